@@ -1,0 +1,181 @@
+"""CPU oracle for the recurrent-cell unroll (fp64, plain C).
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg are the only callers.  The product path (the
+CUDA library and its binding) never imports this package.
+
+The C source ``oracle.c`` is compiled on first use with gcc (``-O2 -fopenmp``,
+portable C, no target-specific flags) into ``oracle/_build/liboracle.so`` and
+loaded with ctypes.  Every function takes numpy arrays and returns float64
+results.  See ``oracle.c`` for the equations and the passages they follow.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+LSTM, GRU = 0, 1
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into a shared library (idempotent)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class _LayerW(ctypes.Structure):
+    _fields_ = [("w_ih", ctypes.c_void_p), ("w_hh", ctypes.c_void_p),
+                ("b_ih", ctypes.c_void_p), ("b_hh", ctypes.c_void_p),
+                ("w_hr", ctypes.c_void_p)]
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i = ctypes.c_int
+            lib.oracle_rnn_forward.restype = i
+            lib.oracle_rnn_forward.argtypes = [i, i, i, i, i, i, i, i, i, P, P, P, P, P, P, P, P,
+                                               P, i, i]
+            lib.oracle_pack.restype = i
+            lib.oracle_pack.argtypes = [i, i, P, P, P, P]
+            lib.oracle_rssm_unroll.restype = i
+            lib.oracle_rssm_unroll.argtypes = [i, i, i, i, i, i] + [P] * 14 + [P, P, P, P, P, i, i]
+            lib.oracle_bf16_round.restype = ctypes.c_double
+            lib.oracle_bf16_round.argtypes = [ctypes.c_float]
+            lib.oracle_num_threads_default.restype = i
+            _lib = lib
+    return _lib
+
+
+def _f32(a):
+    if a is None:
+        return None
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _i32(a):
+    if a is None:
+        return None
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def default_threads() -> int:
+    return int(_load().oracle_num_threads_default())
+
+
+def bf16_round(values) -> np.ndarray:
+    """fp32 -> bf16 (round to nearest even) -> value, as float64."""
+    lib = _load()
+    v = _f32(values).ravel()
+    return np.array([lib.oracle_bf16_round(float(f)) for f in v], dtype=np.float64).reshape(
+        np.shape(values))
+
+
+def pack(lengths, T: int):
+    """Length sort metadata: (sorted_idx, unsorted_idx, batch_sizes), int32."""
+    lib = _load()
+    ln = _i32(lengths)
+    B = ln.shape[0]
+    s = np.zeros(B, np.int32)
+    u = np.zeros(B, np.int32)
+    bs = np.zeros(T, np.int32)
+    rc = lib.oracle_pack(B, T, _ptr(ln), _ptr(s), _ptr(u), _ptr(bs))
+    if rc != 0:
+        raise ValueError("lengths outside [1, T]")
+    return s, u, bs
+
+
+def rnn_forward(cell: int, x, weights, *, hidden: int, proj: int = 0, bidirectional: bool = False,
+                lengths=None, h0=None, c0=None, bf16_weights: bool = False, rows=None,
+                threads: int = 0):
+    """Stacked LSTM / GRU (optionally bidirectional / projected) forward in fp64.
+
+    x: [T, B, in]; weights: list over layer*D + dir of dicts with keys
+    w_ih, w_hh, b_ih, b_hh (None = zero) and w_hr (projection, LSTM only).
+    rows: optional list of batch rows to compute (others are left zero).
+    Returns (y [T,B,D*Hout], h_n [L*D,B,Hout], c_n [L*D,B,H] or None).
+    """
+    lib = _load()
+    x = _f32(x)
+    T, B, in_dim = x.shape
+    D = 2 if bidirectional else 1
+    L = len(weights) // D
+    assert L * D == len(weights) and L >= 1
+    Hout = proj if proj > 0 else hidden
+    keep = []
+    arr = (_LayerW * (L * D))()
+    for i, w in enumerate(weights):
+        vals = [_f32(w.get(k)) for k in ("w_ih", "w_hh", "b_ih", "b_hh", "w_hr")]
+        keep.extend(vals)
+        arr[i] = _LayerW(*[_ptr(v) for v in vals])
+    ln = _i32(lengths)
+    h0a, c0a = _f32(h0), _f32(c0)
+    y = np.zeros((T, B, D * Hout), np.float64)
+    hn = np.zeros((L * D, B, Hout), np.float64)
+    cn = np.zeros((L * D, B, hidden), np.float64)
+    rw = _i32(rows)
+    rc = lib.oracle_rnn_forward(int(cell), int(bidirectional), L, in_dim, hidden, proj,
+                                int(bool(bf16_weights)), T, B, _ptr(x), _ptr(ln), _ptr(h0a),
+                                _ptr(c0a), ctypes.addressof(arr), _ptr(y), _ptr(hn), _ptr(cn),
+                                _ptr(rw), 0 if rw is None else len(rw), int(threads))
+    if rc != 0:
+        raise ValueError("oracle_rnn_forward: invalid arguments")
+    return y, hn, (cn if cell == LSTM else None)
+
+
+def rssm_unroll(weights, actions, eps, *, state0=None, belief0=None, rows=None, threads: int = 0):
+    """RSSM prior unroll (actions given) in fp64.
+
+    weights: dict W1,b1,W_ih,W_hh,b_ih,b_hh,W2,b2,W3,b3 (PyTorch Linear/GRUCell layout).
+    actions [T,B,A], eps [T,B,S].  Returns (means, stds, states, beliefs).
+    """
+    lib = _load()
+    a = _f32(actions)
+    e = _f32(eps)
+    T, B, A = a.shape
+    S = e.shape[2]
+    W = {k: _f32(v) for k, v in weights.items()}
+    Hd = W["W1"].shape[0]
+    RH = W["W_hh"].shape[1]
+    means = np.zeros((T, B, S))
+    stds = np.zeros((T, B, S))
+    states = np.zeros((T, B, S))
+    beliefs = np.zeros((T, B, RH))
+    s0, b0 = _f32(state0), _f32(belief0)
+    rw = _i32(rows)
+    rc = lib.oracle_rssm_unroll(S, A, Hd, RH, T, B, *[_ptr(W[k]) for k in (
+        "W1", "b1", "W_ih", "W_hh", "b_ih", "b_hh", "W2", "b2", "W3", "b3")],
+        _ptr(s0), _ptr(b0), _ptr(a), _ptr(e), _ptr(means), _ptr(stds), _ptr(states),
+        _ptr(beliefs), _ptr(rw), 0 if rw is None else len(rw), int(threads))
+    if rc != 0:
+        raise ValueError("oracle_rssm_unroll: invalid arguments")
+    return means, stds, states, beliefs

@@ -1,0 +1,419 @@
+/*
+ * CPU oracle for the time-unrolled recurrent-cell forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only the tests, the smoke check and the benchmark's CPU
+ * baseline use it.  It shares no code, header or constant with the CUDA
+ * library.
+ *
+ * Everything here is plain fp64 arithmetic over the recurrence as written,
+ * one batch row at a time (rows are independent), with no blocking, fusion
+ * or reordering.  Inputs arrive as the same fp32 bits the GPU receives and
+ * are widened to double; for the bf16-weight path the weights are first
+ * rounded to bf16 (round-to-nearest-even) so that weight quantisation is not
+ * counted as error.
+ *
+ * Sources for what is computed (the pages name the modules, not their
+ * equations; the equations are the standard ones of the modules named):
+ *  - LSTM / LSTM with projection: "Integrating CuDNN API for LSTMs with
+ *    projections" (pytorch/pytorch issue 46213), Pitch and the design reply
+ *    on CellParams: the projected cell is the ordinary LSTM cell followed by
+ *    one more matmul on the resulting hidden state (h = W_hr (o * tanh c)).
+ *  - GRU: the nn.GRUCell named as the core of RSSMPrior in
+ *    "[Feature Request] CUDNN version of RSSM" (pytorch/rl issue 366),
+ *    Motivation and Solution; reset gate applied after the hidden matmul.
+ *  - Variable-length batches, sort by length and packing: "RNN Op Changes
+ *    (was: Variable Length Support for cuDNN RNN)" (apache/mxnet issue 9543),
+ *    first post.  Ties in the length sort keep ascending row order.
+ *  - RSSM prior step and unroll variant 1: pytorch/rl issue 366, Solution
+ *    (RSSMPrior.forward and the first unroll_rssm), with the noise supplied
+ *    as an input tensor and the NormalParamWrapper read as
+ *    mean = p[:S], std = softplus(p[S:]) + scale_lb (scale_lb = 0.1).
+ *
+ * Pins: every function here is checked in tests/test_oracle_pins.py against
+ * closed forms, saturated-gate limits, hand-computed single steps, an
+ * independently written scalar Python evaluation on tiny inputs, invariants
+ * (batch permutation, composition of layers, packed == per-sequence), and an
+ * independent library evaluation (torch float64 on CPU).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define OR_LSTM 0
+#define OR_GRU 1
+
+/* Weights of one layer and direction, PyTorch layout, fp32 bits. */
+typedef struct {
+    const float *w_ih; /* [nG*H, in]   */
+    const float *w_hh; /* [nG*H, Hout] */
+    const float *b_ih; /* [nG*H] or NULL (= zero) */
+    const float *b_hh; /* [nG*H] or NULL (= zero) */
+    const float *w_hr; /* [P, H] or NULL when there is no projection */
+} oracle_layer_w;
+
+/* fp32 -> bf16 -> fp32 with round-to-nearest-even on the bit pattern. */
+static double bf16_rne(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7f800000u) == 0x7f800000u) {          /* inf or nan */
+        if (u & 0x007fffffu) u |= 0x00400000u;        /* quiet nan */
+        u &= 0xffff0000u;
+    } else {
+        uint32_t keep_lsb = (u >> 16) & 1u;
+        u += 0x7fffu + keep_lsb;
+        u &= 0xffff0000u;
+    }
+    float r;
+    memcpy(&r, &u, sizeof r);
+    return (double)r;
+}
+
+/* Widen n fp32 values to double, optionally through bf16 first. NULL -> zeros. */
+static double *widen(const float *src, size_t n, int to_bf16) {
+    double *d = (double *)calloc(n ? n : 1, sizeof(double));
+    if (!d) return NULL;
+    if (src)
+        for (size_t i = 0; i < n; ++i) d[i] = to_bf16 ? bf16_rne(src[i]) : (double)src[i];
+    return d;
+}
+
+double oracle_bf16_round(float f) { return bf16_rne(f); }
+
+static double sigmoid(double v) { return 1.0 / (1.0 + exp(-v)); }
+static double elu(double v) { return v > 0.0 ? v : expm1(v); }
+static double softplus(double v) { return (v > 0.0 ? v : 0.0) + log1p(exp(-fabs(v))); }
+
+/* ---------------------------------------------------------------------- */
+/* Length sort and packing metadata.                                        */
+/* sorted_idx[s]  = original row at sorted position s, ordered by length   */
+/*                  descending, ties by ascending original index;          */
+/* unsorted_idx[b] = sorted position of original row b;                    */
+/* batch_sizes[t] = number of rows whose length exceeds t.                 */
+/* Returns -1 if some length is outside [1, T].                             */
+int oracle_pack(int B, int T, const int32_t *lengths, int32_t *sorted_idx,
+                int32_t *unsorted_idx, int32_t *batch_sizes) {
+    for (int b = 0; b < B; ++b)
+        if (lengths[b] < 1 || lengths[b] > T) return -1;
+    /* plain selection: position of row b = rows that must come before it */
+    for (int b = 0; b < B; ++b) {
+        int pos = 0;
+        for (int o = 0; o < B; ++o)
+            if (lengths[o] > lengths[b] || (lengths[o] == lengths[b] && o < b)) ++pos;
+        sorted_idx[pos] = b;
+        unsorted_idx[b] = pos;
+    }
+    for (int t = 0; t < T; ++t) {
+        int n = 0;
+        for (int b = 0; b < B; ++b)
+            if (lengths[b] > t) ++n;
+        batch_sizes[t] = n;
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* One direction of one layer for one batch row.                            */
+/* in_seq: [len][in_w] input vectors of this row (time order);             */
+/* out:    [T][out_stride] written at column offset col for t < len.       */
+/* h, c:   state, updated in place (c unused for GRU).                     */
+static void run_direction(int cell, int in_w, int H, int P, int len, int reverse,
+                          const double *in_seq, const double *Wih, const double *Whh,
+                          const double *bih, const double *bhh, const double *Whr,
+                          double *h, double *c, double *out, int out_stride, int col,
+                          double *scratch /* [nG*H + H] */) {
+    const int nG = (cell == OR_LSTM) ? 4 : 3;
+    const int Hout = P > 0 ? P : H;
+    double *pre = scratch;          /* nG*H */
+    double *m = scratch + nG * H;   /* H */
+    for (int s = 0; s < len; ++s) {
+        const int t = reverse ? (len - 1 - s) : s;
+        const double *xt = in_seq + (size_t)t * in_w;
+        if (cell == OR_LSTM) {
+            /* gates = W_ih x + b_ih + W_hh h + b_hh, rows ordered i, f, g, o */
+            for (int r = 0; r < nG * H; ++r) {
+                double acc = bih[r] + bhh[r];
+                for (int k = 0; k < in_w; ++k) acc += Wih[(size_t)r * in_w + k] * xt[k];
+                for (int k = 0; k < Hout; ++k) acc += Whh[(size_t)r * Hout + k] * h[k];
+                pre[r] = acc;
+            }
+            for (int j = 0; j < H; ++j) {
+                double ig = sigmoid(pre[0 * H + j]);
+                double fg = sigmoid(pre[1 * H + j]);
+                double gg = tanh(pre[2 * H + j]);
+                double og = sigmoid(pre[3 * H + j]);
+                c[j] = fg * c[j] + ig * gg;
+                m[j] = og * tanh(c[j]);
+            }
+            if (P > 0) {
+                /* projected hidden state h = W_hr m (no bias) */
+                for (int p = 0; p < P; ++p) {
+                    double acc = 0.0;
+                    for (int j = 0; j < H; ++j) acc += Whr[(size_t)p * H + j] * m[j];
+                    h[p] = acc;
+                }
+            } else {
+                for (int j = 0; j < H; ++j) h[j] = m[j];
+            }
+        } else {
+            /* GRU, rows ordered r, z, n; the reset gate multiplies the
+               hidden-side n pre-activation including its bias */
+            double *gi = pre; /* staging for the new h, H entries */
+            for (int j = 0; j < H; ++j) {
+                double ir = bih[0 * H + j], iz = bih[1 * H + j], in_ = bih[2 * H + j];
+                double hr = bhh[0 * H + j], hz = bhh[1 * H + j], hn = bhh[2 * H + j];
+                for (int k = 0; k < in_w; ++k) {
+                    ir += Wih[(size_t)(0 * H + j) * in_w + k] * xt[k];
+                    iz += Wih[(size_t)(1 * H + j) * in_w + k] * xt[k];
+                    in_ += Wih[(size_t)(2 * H + j) * in_w + k] * xt[k];
+                }
+                for (int k = 0; k < H; ++k) {
+                    hr += Whh[(size_t)(0 * H + j) * H + k] * h[k];
+                    hz += Whh[(size_t)(1 * H + j) * H + k] * h[k];
+                    hn += Whh[(size_t)(2 * H + j) * H + k] * h[k];
+                }
+                double rg = sigmoid(ir + hr);
+                double zg = sigmoid(iz + hz);
+                double ng = tanh(in_ + rg * hn);
+                gi[j] = (1.0 - zg) * ng + zg * h[j]; /* new h, staged */
+            }
+            for (int j = 0; j < H; ++j) h[j] = gi[j];
+        }
+        double *ot = out + (size_t)t * out_stride + col;
+        for (int k = 0; k < Hout; ++k) ot[k] = h[k];
+    }
+}
+
+/*
+ * Full forward of a stacked (optionally bidirectional, optionally projected)
+ * LSTM or GRU, restricted to the batch rows listed in `rows` (all rows when
+ * rows == NULL).  Rows are independent, so the restriction computes exactly
+ * the same values for the listed rows.
+ *
+ * x        [T, B, in]          fp32
+ * lengths  [B] or NULL (all T)
+ * h0       [L*D, B, Hout] or NULL (zeros);  c0 [L*D, B, H] or NULL (zeros)
+ * w        [L*D] weight sets, index l*D + d
+ * y        [T, B, D*Hout] double; rows listed are fully written (zeros past length)
+ * h_n      [L*D, B, Hout] double or NULL;  c_n [L*D, B, H] double or NULL
+ * Returns 0, or -1 on invalid arguments.
+ */
+int oracle_rnn_forward(int cell, int bidir, int layers, int in_dim, int hidden, int proj,
+                       int bf16_weights, int T, int B, const float *x, const int32_t *lengths,
+                       const float *h0, const float *c0, const oracle_layer_w *w, double *y,
+                       double *h_n, double *c_n, const int32_t *rows, int nrows, int nthreads) {
+    if (cell != OR_LSTM && cell != OR_GRU) return -1;
+    if (layers < 1 || in_dim < 1 || hidden < 1 || T < 0 || B < 0) return -1;
+    if (proj < 0 || (proj > 0 && cell != OR_LSTM)) return -1;
+    const int D = bidir ? 2 : 1;
+    const int H = hidden, P = proj, Hout = proj > 0 ? proj : hidden;
+    const int nG = (cell == OR_LSTM) ? 4 : 3;
+    if (lengths)
+        for (int b = 0; b < B; ++b)
+            if (lengths[b] < 1 || lengths[b] > T) return -1;
+    const int nsel = rows ? nrows : B;
+
+    /* widen all weights once (shared read-only by all threads) */
+    const int LD = layers * D;
+    double **Wih = (double **)calloc(LD, sizeof(double *));
+    double **Whh = (double **)calloc(LD, sizeof(double *));
+    double **bih = (double **)calloc(LD, sizeof(double *));
+    double **bhh = (double **)calloc(LD, sizeof(double *));
+    double **Whr = (double **)calloc(LD, sizeof(double *));
+    for (int l = 0; l < layers; ++l) {
+        const int in_w = (l == 0) ? in_dim : D * Hout;
+        for (int d = 0; d < D; ++d) {
+            const int i = l * D + d;
+            Wih[i] = widen(w[i].w_ih, (size_t)nG * H * in_w, bf16_weights);
+            Whh[i] = widen(w[i].w_hh, (size_t)nG * H * Hout, bf16_weights);
+            /* biases stay fp32 on both paths */
+            bih[i] = widen(w[i].b_ih, (size_t)nG * H, 0);
+            bhh[i] = widen(w[i].b_hh, (size_t)nG * H, 0);
+            Whr[i] = P > 0 ? widen(w[i].w_hr, (size_t)P * H, bf16_weights) : NULL;
+        }
+    }
+
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel
+#endif
+    {
+        const int wmax = (in_dim > D * Hout ? in_dim : D * Hout);
+        double *seq_a = (double *)malloc((size_t)(T ? T : 1) * wmax * sizeof(double));
+        double *seq_b = (double *)malloc((size_t)(T ? T : 1) * D * Hout * sizeof(double));
+        double *h = (double *)malloc((size_t)Hout * sizeof(double));
+        double *c = (double *)malloc((size_t)H * sizeof(double));
+        double *scratch = (double *)malloc((size_t)(nG * H + H + nG * H) * sizeof(double));
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int q = 0; q < nsel; ++q) {
+            const int b = rows ? rows[q] : q;
+            const int len = lengths ? lengths[b] : T;
+            /* layer-0 input sequence of this row */
+            for (int t = 0; t < len; ++t)
+                for (int k = 0; k < in_dim; ++k)
+                    seq_a[(size_t)t * in_dim + k] = (double)x[((size_t)t * B + b) * in_dim + k];
+            int in_w = in_dim;
+            for (int l = 0; l < layers; ++l) {
+                for (int d = 0; d < D; ++d) {
+                    const int i = l * D + d;
+                    for (int k = 0; k < Hout; ++k)
+                        h[k] = h0 ? (double)h0[((size_t)i * B + b) * Hout + k] : 0.0;
+                    for (int k = 0; k < H; ++k)
+                        c[k] = c0 ? (double)c0[((size_t)i * B + b) * H + k] : 0.0;
+                    run_direction(cell, in_w, H, P, len, d == 1, seq_a, Wih[i], Whh[i], bih[i],
+                                  bhh[i], Whr[i], h, c, seq_b, D * Hout, d * Hout, scratch);
+                    if (h_n)
+                        for (int k = 0; k < Hout; ++k) h_n[((size_t)i * B + b) * Hout + k] = h[k];
+                    if (c_n && cell == OR_LSTM)
+                        for (int k = 0; k < H; ++k) c_n[((size_t)i * B + b) * H + k] = c[k];
+                }
+                /* this layer's output is the next layer's input */
+                in_w = D * Hout;
+                memcpy(seq_a, seq_b, (size_t)len * in_w * sizeof(double));
+            }
+            for (int t = 0; t < T; ++t)
+                for (int k = 0; k < D * Hout; ++k)
+                    y[((size_t)t * B + b) * D * Hout + k] =
+                        t < len ? seq_a[(size_t)t * D * Hout + k] : 0.0;
+        }
+        free(seq_a);
+        free(seq_b);
+        free(h);
+        free(c);
+        free(scratch);
+    }
+    for (int i = 0; i < LD; ++i) {
+        free(Wih[i]);
+        free(Whh[i]);
+        free(bih[i]);
+        free(bhh[i]);
+        free(Whr[i]);
+    }
+    free(Wih);
+    free(Whh);
+    free(bih);
+    free(bhh);
+    free(Whr);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* RSSM prior unroll with given actions (unroll variant 1).                 */
+/*                                                                          */
+/* Per step:  a      = ELU(W1 [state, action] + b1)           (width Hd)    */
+/*            belief = GRUCell(a, belief)                     (width RH)    */
+/*            q      = ELU(W2 belief + b2)                    (width Hd)    */
+/*            p      = W3 q + b3                              (width 2S)    */
+/*            mean = p[:S];  std = softplus(p[S:]) + 0.1;                   */
+/*            state = mean + eps_t * std                                    */
+/* Outputs at step t are those after the step's update.                    */
+/* Layouts: W1 [Hd, S+A] (state columns first), Wih [3RH, Hd],              */
+/* Whh [3RH, RH], W2 [Hd, RH], W3 [2S, Hd]; actions [T,B,A], eps [T,B,S],   */
+/* state0 [B,S], belief0 [B,RH] (NULL = zeros); means/stds/states [T,B,S],  */
+/* beliefs [T,B,RH].                                                        */
+int oracle_rssm_unroll(int S, int A, int Hd, int RH, int T, int B, const float *W1,
+                       const float *b1, const float *Wih, const float *Whh, const float *bih,
+                       const float *bhh, const float *W2, const float *b2, const float *W3,
+                       const float *b3, const float *state0, const float *belief0,
+                       const float *actions, const float *eps, double *means, double *stds,
+                       double *states, double *beliefs, const int32_t *rows, int nrows,
+                       int nthreads) {
+    if (S < 1 || A < 0 || Hd < 1 || RH < 1 || T < 0 || B < 0) return -1;
+    const int nsel = rows ? nrows : B;
+    double *w1 = widen(W1, (size_t)Hd * (S + A), 0), *vb1 = widen(b1, Hd, 0);
+    double *wih = widen(Wih, (size_t)3 * RH * Hd, 0), *whh = widen(Whh, (size_t)3 * RH * RH, 0);
+    double *vbih = widen(bih, (size_t)3 * RH, 0), *vbhh = widen(bhh, (size_t)3 * RH, 0);
+    double *w2 = widen(W2, (size_t)Hd * RH, 0), *vb2 = widen(b2, Hd, 0);
+    double *w3 = widen(W3, (size_t)2 * S * Hd, 0), *vb3 = widen(b3, (size_t)2 * S, 0);
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel
+#endif
+    {
+        double *state = (double *)malloc((size_t)S * sizeof(double));
+        double *bel = (double *)malloc((size_t)RH * sizeof(double));
+        double *nbel = (double *)malloc((size_t)RH * sizeof(double));
+        double *a = (double *)malloc((size_t)Hd * sizeof(double));
+        double *q = (double *)malloc((size_t)Hd * sizeof(double));
+        double *p = (double *)malloc((size_t)2 * S * sizeof(double));
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int qi = 0; qi < nsel; ++qi) {
+            const int b = rows ? rows[qi] : qi;
+            for (int j = 0; j < S; ++j) state[j] = state0 ? (double)state0[(size_t)b * S + j] : 0.0;
+            for (int j = 0; j < RH; ++j)
+                bel[j] = belief0 ? (double)belief0[(size_t)b * RH + j] : 0.0;
+            for (int t = 0; t < T; ++t) {
+                const float *act = actions + ((size_t)t * B + b) * A;
+                for (int i = 0; i < Hd; ++i) {
+                    double u = vb1[i];
+                    for (int j = 0; j < S; ++j) u += w1[(size_t)i * (S + A) + j] * state[j];
+                    for (int j = 0; j < A; ++j) u += w1[(size_t)i * (S + A) + S + j] * (double)act[j];
+                    a[i] = elu(u);
+                }
+                for (int j = 0; j < RH; ++j) {
+                    double ir = vbih[j], iz = vbih[RH + j], in_ = vbih[2 * RH + j];
+                    double hr = vbhh[j], hz = vbhh[RH + j], hn = vbhh[2 * RH + j];
+                    for (int k = 0; k < Hd; ++k) {
+                        ir += wih[(size_t)j * Hd + k] * a[k];
+                        iz += wih[(size_t)(RH + j) * Hd + k] * a[k];
+                        in_ += wih[(size_t)(2 * RH + j) * Hd + k] * a[k];
+                    }
+                    for (int k = 0; k < RH; ++k) {
+                        hr += whh[(size_t)j * RH + k] * bel[k];
+                        hz += whh[(size_t)(RH + j) * RH + k] * bel[k];
+                        hn += whh[(size_t)(2 * RH + j) * RH + k] * bel[k];
+                    }
+                    double rg = sigmoid(ir + hr), zg = sigmoid(iz + hz);
+                    double ng = tanh(in_ + rg * hn);
+                    nbel[j] = (1.0 - zg) * ng + zg * bel[j];
+                }
+                memcpy(bel, nbel, (size_t)RH * sizeof(double));
+                for (int i = 0; i < Hd; ++i) {
+                    double v = vb2[i];
+                    for (int k = 0; k < RH; ++k) v += w2[(size_t)i * RH + k] * bel[k];
+                    q[i] = elu(v);
+                }
+                for (int i = 0; i < 2 * S; ++i) {
+                    double v = vb3[i];
+                    for (int k = 0; k < Hd; ++k) v += w3[(size_t)i * Hd + k] * q[k];
+                    p[i] = v;
+                }
+                const size_t o = ((size_t)t * B + b) * S;
+                for (int j = 0; j < S; ++j) {
+                    const double mean = p[j];
+                    const double sd = softplus(p[S + j]) + 0.1;
+                    state[j] = mean + (double)eps[o + j] * sd;
+                    means[o + j] = mean;
+                    stds[o + j] = sd;
+                    states[o + j] = state[j];
+                }
+                for (int j = 0; j < RH; ++j) beliefs[((size_t)t * B + b) * RH + j] = bel[j];
+            }
+        }
+        free(state);
+        free(bel);
+        free(nbel);
+        free(a);
+        free(q);
+        free(p);
+    }
+    free(w1); free(vb1); free(wih); free(whh); free(vbih); free(vbhh);
+    free(w2); free(vb2); free(w3); free(vb3);
+    return 0;
+}
+
+int oracle_num_threads_default(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,532 @@
+"""Pins for the CPU oracle: it is checked against things other than itself.
+
+- closed forms (zero weights, saturated gates) derived from the cell equations;
+- an independent library evaluation (torch float64 on CPU: nn.LSTM with
+  proj_size, nn.GRU, nn.GRUCell, pack_padded_sequence) of the modules the
+  pages name (pytorch/rl issue 366 Solution; pytorch/pytorch issue 46213);
+- invariants (layer composition, reversal for the backward direction,
+  packed == per-sequence, batch permutation, identity projection);
+- a separately written scalar evaluation on tiny inputs;
+- hand-worked golden fixtures under tests/golden/.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from recurrent_cell_unroll_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _zero_weights(cell, layers, in_dim, H, D=1, proj=0):
+    nG = 4 if cell == oracle.LSTM else 3
+    Hout = proj or H
+    ws = []
+    for layer in range(layers):
+        in_w = in_dim if layer == 0 else D * Hout
+        for _ in range(D):
+            ws.append({"w_ih": np.zeros((nG * H, in_w), np.float32),
+                       "w_hh": np.zeros((nG * H, Hout), np.float32),
+                       "b_ih": None, "b_hh": None,
+                       "w_hr": np.zeros((proj, H), np.float32) if proj else None})
+    return ws
+
+
+def _rand_weights(rng, cell, layers, in_dim, H, D=1, proj=0, scale=0.5):
+    nG = 4 if cell == oracle.LSTM else 3
+    Hout = proj or H
+    ws = []
+    for layer in range(layers):
+        in_w = in_dim if layer == 0 else D * Hout
+        for _ in range(D):
+            ws.append({"w_ih": rng.uniform(-scale, scale, (nG * H, in_w)).astype(np.float32),
+                       "w_hh": rng.uniform(-scale, scale, (nG * H, Hout)).astype(np.float32),
+                       "b_ih": rng.uniform(-scale, scale, nG * H).astype(np.float32),
+                       "b_hh": rng.uniform(-scale, scale, nG * H).astype(np.float32),
+                       "w_hr": rng.uniform(-scale, scale, (proj, H)).astype(np.float32)
+                       if proj else None})
+    return ws
+
+
+# --------------------------------------------------------------------------- bf16 rounding
+
+def test_bf16_round_matches_library():
+    rng = np.random.default_rng(1)
+    v = np.concatenate([rng.standard_normal(2000).astype(np.float32),
+                        # exact ties: low 16 bits 0x8000, both parities of bit 16
+                        np.array([0x3f808000, 0x3f818000, 0xbf808000, 0x40490fdb, 0x00018000],
+                                 dtype=np.uint32).view(np.float32)])
+    ours = oracle.bf16_round(v)
+    ref = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_bf16_weights_flag_equals_prerounded_weights():
+    rng = np.random.default_rng(2)
+    ws = _rand_weights(rng, oracle.LSTM, 1, 5, 4, proj=3)
+    x = rng.standard_normal((6, 2, 5)).astype(np.float32)
+    y1, h1, c1 = oracle.rnn_forward(oracle.LSTM, x, ws, hidden=4, proj=3, bf16_weights=True)
+    pre = [{k: (None if v is None or k.startswith("b_") else
+                torch.from_numpy(v).to(torch.bfloat16).float().numpy()) if k != "b_ih" and k != "b_hh"
+            else v for k, v in w.items()} for w in ws]
+    y2, h2, c2 = oracle.rnn_forward(oracle.LSTM, x, pre, hidden=4, proj=3)
+    assert np.array_equal(y1, y2) and np.array_equal(h1, h2) and np.array_equal(c1, c2)
+    # and rounding really changes something
+    y3, _, _ = oracle.rnn_forward(oracle.LSTM, x, ws, hidden=4, proj=3)
+    assert not np.array_equal(y1, y3)
+
+
+# --------------------------------------------------------------------------- closed forms
+
+def test_lstm_zero_weights_closed_form():
+    """Zero weights: i=f=o=1/2, g=0, so c_t = 2^-t c0 and h_t = tanh(c_t)/2."""
+    T, B, H = 6, 3, 4
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((T, B, 2)).astype(np.float32)
+    h0 = rng.standard_normal((1, B, H)).astype(np.float32)
+    c0 = rng.standard_normal((1, B, H)).astype(np.float32)
+    y, hn, cn = oracle.rnn_forward(oracle.LSTM, x, _zero_weights(oracle.LSTM, 1, 2, H),
+                                   hidden=H, h0=h0, c0=c0)
+    for t in range(T):
+        c_t = c0[0].astype(np.float64) * 2.0 ** -(t + 1)
+        np.testing.assert_allclose(y[t], 0.5 * np.tanh(c_t), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(cn[0], c0[0] * 2.0 ** -T, rtol=0, atol=1e-15)
+
+
+def test_lstm_saturated_forget_keeps_cell():
+    """b_f = +40, b_i = -40: f = 1, i = 0 to double precision, so c_t = c0."""
+    T, B, H, I = 7, 2, 3, 4
+    rng = np.random.default_rng(4)
+    ws = _rand_weights(rng, oracle.LSTM, 1, I, H, scale=0.3)
+    ws[0]["b_ih"][0:H] = -40.0
+    ws[0]["b_ih"][H:2 * H] = 40.0
+    x = rng.standard_normal((T, B, I)).astype(np.float32)
+    c0 = rng.standard_normal((1, B, H)).astype(np.float32)
+    _, _, cn = oracle.rnn_forward(oracle.LSTM, x, ws, hidden=H, c0=c0)
+    np.testing.assert_allclose(cn[0], c0[0], rtol=0, atol=1e-15)
+
+
+def test_lstm_input_path_only():
+    """W_hh = 0, i = o = 1, f = 0: h_t = tanh(tanh(W_ig x_t + b_ig + b_hg))."""
+    T, B, H, I = 5, 2, 3, 4
+    rng = np.random.default_rng(5)
+    ws = _rand_weights(rng, oracle.LSTM, 1, I, H)
+    ws[0]["w_hh"][:] = 0
+    ws[0]["b_ih"][0:H] = 40.0
+    ws[0]["b_ih"][H:2 * H] = -40.0
+    ws[0]["b_ih"][3 * H:4 * H] = 40.0
+    x = rng.standard_normal((T, B, I)).astype(np.float32)
+    y, _, _ = oracle.rnn_forward(oracle.LSTM, x, ws, hidden=H)
+    Wg = ws[0]["w_ih"][2 * H:3 * H].astype(np.float64)
+    bg = ws[0]["b_ih"][2 * H:3 * H].astype(np.float64) + ws[0]["b_hh"][2 * H:3 * H]
+    expect = np.tanh(np.tanh(np.einsum("hk,tbk->tbh", Wg, x.astype(np.float64)) + bg))
+    np.testing.assert_allclose(y, expect, rtol=0, atol=1e-14)
+
+
+def test_gru_zero_weights_closed_form():
+    """Zero weights: r = z = 1/2, n = 0, so h_t = 2^-t h0."""
+    T, B, H = 6, 3, 5
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((T, B, 2)).astype(np.float32)
+    h0 = rng.standard_normal((1, B, H)).astype(np.float32)
+    y, hn, _ = oracle.rnn_forward(oracle.GRU, x, _zero_weights(oracle.GRU, 1, 2, H),
+                                  hidden=H, h0=h0)
+    for t in range(T):
+        np.testing.assert_allclose(y[t], h0[0] * 2.0 ** -(t + 1), rtol=0, atol=1e-15)
+
+
+def test_gru_update_gate_limits():
+    """z -> 1 keeps h0 exactly; z -> 0 gives h_t = n_t."""
+    T, B, H, I = 4, 2, 3, 2
+    rng = np.random.default_rng(7)
+    ws = _rand_weights(rng, oracle.GRU, 1, I, H, scale=0.3)
+    x = rng.standard_normal((T, B, I)).astype(np.float32)
+    h0 = rng.standard_normal((1, B, H)).astype(np.float32)
+    ws[0]["b_ih"][H:2 * H] = 40.0
+    y, _, _ = oracle.rnn_forward(oracle.GRU, x, ws, hidden=H, h0=h0)
+    for t in range(T):
+        np.testing.assert_allclose(y[t], h0[0], rtol=0, atol=1e-15)
+    # z -> 0 and W_hh = 0: h_t = tanh(W_in x_t + b_in + r * b_hn), r = sigma(W_ir x + b_ir + b_hr)
+    ws[0]["b_ih"][H:2 * H] = -40.0
+    ws[0]["w_hh"][:] = 0
+    y, _, _ = oracle.rnn_forward(oracle.GRU, x, ws, hidden=H, h0=h0)
+    xd = x.astype(np.float64)
+    Wi, bi, bh = ws[0]["w_ih"].astype(np.float64), ws[0]["b_ih"], ws[0]["b_hh"]
+    r = 1 / (1 + np.exp(-(xd @ Wi[0:H].T + bi[0:H] + bh[0:H])))
+    n = np.tanh(xd @ Wi[2 * H:].T + bi[2 * H:] + r * bh[2 * H:])
+    np.testing.assert_allclose(y, n, rtol=0, atol=1e-14)
+
+
+def test_lstm_one_step_by_hand():
+    """H = 1, in = 1, T = 1 with simple numbers, evaluated step by step."""
+    w = {"w_ih": np.array([[0.5], [-0.25], [1.0], [0.75]], np.float32),
+         "w_hh": np.array([[0.125], [0.25], [-0.5], [1.0]], np.float32),
+         "b_ih": np.array([0.0, 1.0, 0.0, -0.5], np.float32),
+         "b_hh": np.array([0.25, 0.0, 0.5, 0.0], np.float32), "w_hr": None}
+    x = np.array([[[2.0]]], np.float32)
+    h0 = np.array([[[0.5]]], np.float32)
+    c0 = np.array([[[-1.0]]], np.float32)
+    y, hn, cn = oracle.rnn_forward(oracle.LSTM, x, [w], hidden=1, h0=h0, c0=c0)
+    s = lambda v: 1.0 / (1.0 + math.exp(-v))
+    i = s(0.5 * 2 + 0.125 * 0.5 + 0.25)        # 1.3125
+    f = s(-0.25 * 2 + 0.25 * 0.5 + 1.0)        # 0.625
+    g = math.tanh(1.0 * 2 - 0.5 * 0.5 + 0.5)   # 2.25
+    o = s(0.75 * 2 + 1.0 * 0.5 - 0.5)          # 1.5
+    c = f * -1.0 + i * g
+    assert abs(cn[0, 0, 0] - c) < 1e-15
+    assert abs(y[0, 0, 0] - o * math.tanh(c)) < 1e-15
+
+
+# --------------------------------------------------------------------------- library cross-check
+
+def _torch_rnn(cell, ws, x, H, proj, D, layers, lengths, h0, c0):
+    in_dim = x.shape[2]
+    kw = dict(input_size=in_dim, hidden_size=H, num_layers=layers, bidirectional=D == 2,
+              dtype=torch.float64)
+    mod = torch.nn.LSTM(proj_size=proj, **kw) if cell == oracle.LSTM else torch.nn.GRU(**kw)
+    with torch.no_grad():
+        for layer in range(layers):
+            for d in range(D):
+                sfx = f"_l{layer}" + ("_reverse" if d else "")
+                w = ws[layer * D + d]
+                getattr(mod, "weight_ih" + sfx).copy_(torch.from_numpy(w["w_ih"]).double())
+                getattr(mod, "weight_hh" + sfx).copy_(torch.from_numpy(w["w_hh"]).double())
+                getattr(mod, "bias_ih" + sfx).copy_(torch.from_numpy(w["b_ih"]).double())
+                getattr(mod, "bias_hh" + sfx).copy_(torch.from_numpy(w["b_hh"]).double())
+                if proj:
+                    getattr(mod, "weight_hr" + sfx).copy_(torch.from_numpy(w["w_hr"]).double())
+        xt = torch.from_numpy(x).double()
+        Hout = proj or H
+        B = x.shape[1]
+        hz = torch.zeros(layers * D, B, Hout, dtype=torch.float64) if h0 is None else \
+            torch.from_numpy(h0).double()
+        cz = torch.zeros(layers * D, B, H, dtype=torch.float64) if c0 is None else \
+            torch.from_numpy(c0).double()
+        state = (hz, cz) if cell == oracle.LSTM else hz
+        if lengths is not None:
+            packed = torch.nn.utils.rnn.pack_padded_sequence(
+                xt, torch.from_numpy(lengths).long(), enforce_sorted=False)
+            out, st = mod(packed, state)
+            y, _ = torch.nn.utils.rnn.pad_packed_sequence(out, total_length=x.shape[0])
+        else:
+            y, st = mod(xt, state)
+    if cell == oracle.LSTM:
+        return y.numpy(), st[0].numpy(), st[1].numpy()
+    return y.numpy(), st.numpy(), None
+
+
+@pytest.mark.parametrize("cell,proj,D,layers,varlen", [
+    (oracle.LSTM, 0, 1, 1, False),
+    (oracle.LSTM, 0, 2, 2, True),
+    (oracle.LSTM, 3, 1, 2, False),
+    (oracle.LSTM, 3, 2, 1, True),
+    (oracle.GRU, 0, 1, 3, False),
+    (oracle.GRU, 0, 2, 2, True),
+])
+def test_against_torch_float64(cell, proj, D, layers, varlen):
+    rng = np.random.default_rng(10 + layers + 3 * D + proj)
+    T, B, I, H = 7, 5, 4, 6
+    ws = _rand_weights(rng, cell, layers, I, H, D=D, proj=proj)
+    x = rng.standard_normal((T, B, I)).astype(np.float32)
+    Hout = proj or H
+    h0 = rng.standard_normal((layers * D, B, Hout)).astype(np.float32)
+    c0 = rng.standard_normal((layers * D, B, H)).astype(np.float32)
+    lengths = rng.integers(1, T + 1, B).astype(np.int32) if varlen else None
+    if varlen:
+        lengths[0] = T
+    y, hn, cn = oracle.rnn_forward(cell, x, ws, hidden=H, proj=proj, bidirectional=D == 2,
+                                   lengths=lengths, h0=h0, c0=c0 if cell == oracle.LSTM else None)
+    ty, thn, tcn = _torch_rnn(cell, ws, x, H, proj, D, layers, lengths, h0,
+                              c0 if cell == oracle.LSTM else None)
+    np.testing.assert_allclose(y, ty, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(hn, thn, rtol=0, atol=1e-12)
+    if cell == oracle.LSTM:
+        np.testing.assert_allclose(cn, tcn, rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------- invariants
+
+def test_identity_projection_equals_plain_lstm():
+    rng = np.random.default_rng(20)
+    T, B, I, H = 6, 3, 4, 5
+    ws = _rand_weights(rng, oracle.LSTM, 2, I, H, proj=H)
+    for w in ws:
+        w["w_hr"] = np.eye(H, dtype=np.float32)
+    plain = [{k: (None if k == "w_hr" else v) for k, v in w.items()} for w in ws]
+    x = rng.standard_normal((T, B, I)).astype(np.float32)
+    y1, h1, c1 = oracle.rnn_forward(oracle.LSTM, x, ws, hidden=H, proj=H)
+    y2, h2, c2 = oracle.rnn_forward(oracle.LSTM, x, plain, hidden=H)
+    assert np.array_equal(y1, y2) and np.array_equal(h1, h2) and np.array_equal(c1, c2)
+
+
+@pytest.mark.parametrize("cell", [oracle.LSTM, oracle.GRU])
+def test_layers_compose(cell):
+    rng = np.random.default_rng(21)
+    T, B, I, H = 5, 3, 4, 6
+    ws = _rand_weights(rng, cell, 2, I, H, D=2)
+    x = rng.standard_normal((T, B, I)).astype(np.float32)
+    y, hn, cn = oracle.rnn_forward(cell, x, ws, hidden=H, bidirectional=True)
+    y1, hn1, cn1 = oracle.rnn_forward(cell, x, ws[:2], hidden=H, bidirectional=True)
+    # layer 2 sees layer 1's output; round-trip via float32 is exact only in fp64, so
+    # compare layer 2 run on the float64 output cast to fp32 with a loose bound
+    y2, hn2, _ = oracle.rnn_forward(cell, y1.astype(np.float32), ws[2:], hidden=H,
+                                    bidirectional=True)
+    np.testing.assert_allclose(hn[:2], hn1, rtol=0, atol=0)
+    np.testing.assert_allclose(y, y2, rtol=0, atol=1e-6)
+    np.testing.assert_allclose(hn[2:], hn2, rtol=0, atol=1e-6)
+
+
+@pytest.mark.parametrize("cell", [oracle.LSTM, oracle.GRU])
+def test_backward_direction_is_reversed_forward(cell):
+    rng = np.random.default_rng(22)
+    T, B, I, H = 6, 4, 3, 5
+    ws = _rand_weights(rng, cell, 1, I, H, D=2)
+    x = rng.standard_normal((T, B, I)).astype(np.float32)
+    lengths = np.array([6, 3, 5, 1], np.int32)
+    y, hn, _ = oracle.rnn_forward(cell, x, ws, hidden=H, bidirectional=True, lengths=lengths)
+    for b in range(B):
+        L = lengths[b]
+        xr = x[:L, b:b + 1][::-1].copy()
+        yr, hr, _ = oracle.rnn_forward(cell, xr, [ws[1]], hidden=H)
+        np.testing.assert_array_equal(y[:L, b, H:], yr[::-1, 0])
+        np.testing.assert_array_equal(hn[1, b], hr[0, 0])
+        yf, hf, _ = oracle.rnn_forward(cell, x[:L, b:b + 1], [ws[0]], hidden=H)
+        np.testing.assert_array_equal(y[:L, b, :H], yf[:, 0])
+        np.testing.assert_array_equal(hn[0, b], hf[0, 0])
+        assert np.all(y[L:, b] == 0)
+
+
+@pytest.mark.parametrize("cell,proj", [(oracle.LSTM, 0), (oracle.LSTM, 2), (oracle.GRU, 0)])
+def test_varlen_equals_per_sequence(cell, proj):
+    rng = np.random.default_rng(23)
+    T, B, I, H = 8, 5, 3, 4
+    ws = _rand_weights(rng, cell, 2, I, H, proj=proj)
+    x = rng.standard_normal((T, B, I)).astype(np.float32)
+    lengths = np.array([8, 2, 5, 5, 1], np.int32)
+    y, hn, cn = oracle.rnn_forward(cell, x, ws, hidden=H, proj=proj, lengths=lengths)
+    for b in range(B):
+        L = lengths[b]
+        yb, hb, cb = oracle.rnn_forward(cell, x[:L, b:b + 1], ws, hidden=H, proj=proj)
+        np.testing.assert_array_equal(y[:L, b], yb[:, 0])
+        np.testing.assert_array_equal(hn[:, b], hb[:, 0])
+        if cn is not None:
+            np.testing.assert_array_equal(cn[:, b], cb[:, 0])
+        assert np.all(y[L:, b] == 0)
+
+
+def test_batch_permutation_and_row_subset():
+    rng = np.random.default_rng(24)
+    T, B, I, H = 5, 6, 3, 4
+    ws = _rand_weights(rng, oracle.GRU, 2, I, H, D=2)
+    x = rng.standard_normal((T, B, I)).astype(np.float32)
+    h0 = rng.standard_normal((4, B, H)).astype(np.float32)
+    lengths = np.array([5, 1, 3, 3, 4, 2], np.int32)
+    y, hn, _ = oracle.rnn_forward(oracle.GRU, x, ws, hidden=H, bidirectional=True,
+                                  lengths=lengths, h0=h0)
+    perm = rng.permutation(B)
+    yp, hnp, _ = oracle.rnn_forward(oracle.GRU, x[:, perm], ws, hidden=H, bidirectional=True,
+                                    lengths=lengths[perm], h0=h0[:, perm])
+    np.testing.assert_array_equal(yp, y[:, perm])
+    np.testing.assert_array_equal(hnp, hn[:, perm])
+    ys, hs, _ = oracle.rnn_forward(oracle.GRU, x, ws, hidden=H, bidirectional=True,
+                                   lengths=lengths, h0=h0, rows=[4, 1])
+    np.testing.assert_array_equal(ys[:, [4, 1]], y[:, [4, 1]])
+    np.testing.assert_array_equal(hs[:, [4, 1]], hn[:, [4, 1]])
+
+
+# --------------------------------------------------------------------------- separately written scalar loops
+
+def _scalar_lstm(w, xs, h, c, proj):
+    """Independent scalar evaluation of one LSTM(P) direction over a list of steps."""
+    H = len(c)
+    out = []
+    for xv in xs:
+        def row(r):
+            v = float(w["b_ih"][r]) + float(w["b_hh"][r])
+            v += sum(float(w["w_ih"][r][k]) * xv[k] for k in range(len(xv)))
+            v += sum(float(w["w_hh"][r][k]) * h[k] for k in range(len(h)))
+            return v
+        sg = lambda v: 1.0 / (1.0 + math.exp(-v))
+        m = []
+        newc = []
+        for j in range(H):
+            ig, fg, gg, og = sg(row(j)), sg(row(H + j)), math.tanh(row(2 * H + j)), sg(row(3 * H + j))
+            cj = fg * c[j] + ig * gg
+            newc.append(cj)
+            m.append(og * math.tanh(cj))
+        c = newc
+        if proj:
+            h = [sum(float(w["w_hr"][p][j]) * m[j] for j in range(H)) for p in range(proj)]
+        else:
+            h = m
+        out.append(list(h))
+    return out, h, c
+
+
+def _scalar_gru(w, xs, h):
+    H = len(h)
+    out = []
+    for xv in xs:
+        def dot(mat, r, vec):
+            return sum(float(mat[r][k]) * vec[k] for k in range(len(vec)))
+        sg = lambda v: 1.0 / (1.0 + math.exp(-v))
+        new = []
+        for j in range(H):
+            r = sg(dot(w["w_ih"], j, xv) + float(w["b_ih"][j]) + dot(w["w_hh"], j, h) + float(w["b_hh"][j]))
+            z = sg(dot(w["w_ih"], H + j, xv) + float(w["b_ih"][H + j]) + dot(w["w_hh"], H + j, h)
+                   + float(w["b_hh"][H + j]))
+            n = math.tanh(dot(w["w_ih"], 2 * H + j, xv) + float(w["b_ih"][2 * H + j])
+                          + r * (dot(w["w_hh"], 2 * H + j, h) + float(w["b_hh"][2 * H + j])))
+            new.append((1 - z) * n + z * h[j])
+        h = new
+        out.append(list(h))
+    return out, h
+
+
+@pytest.mark.parametrize("cell,proj", [(oracle.LSTM, 0), (oracle.LSTM, 2), (oracle.GRU, 0)])
+def test_tiny_scalar_bruteforce(cell, proj):
+    rng = np.random.default_rng(30 + proj)
+    T, B, I, H = 4, 2, 2, 3
+    ws = _rand_weights(rng, cell, 1, I, H, proj=proj)
+    x = rng.standard_normal((T, B, I)).astype(np.float32)
+    Hout = proj or H
+    h0 = rng.standard_normal((1, B, Hout)).astype(np.float32)
+    c0 = rng.standard_normal((1, B, H)).astype(np.float32)
+    y, hn, cn = oracle.rnn_forward(cell, x, ws, hidden=H, proj=proj, h0=h0,
+                                   c0=c0 if cell == oracle.LSTM else None)
+    for b in range(B):
+        xs = [[float(v) for v in x[t, b]] for t in range(T)]
+        if cell == oracle.LSTM:
+            out, h, c = _scalar_lstm(ws[0], xs, [float(v) for v in h0[0, b]],
+                                     [float(v) for v in c0[0, b]], proj)
+            np.testing.assert_allclose(cn[0, b], c, rtol=0, atol=1e-13)
+        else:
+            out, h = _scalar_gru(ws[0], xs, [float(v) for v in h0[0, b]])
+        np.testing.assert_allclose(y[:, b], np.array(out), rtol=0, atol=1e-13)
+        np.testing.assert_allclose(hn[0, b], h, rtol=0, atol=1e-13)
+
+
+# --------------------------------------------------------------------------- packing
+
+def test_pack_golden_example():
+    g = json.load(open(os.path.join(GOLDEN, "pack_example.json")))
+    s, u, bs = oracle.pack(np.array(g["lengths"], np.int32), g["T"])
+    assert s.tolist() == g["sorted_idx"]
+    assert u.tolist() == g["unsorted_idx"]
+    assert bs.tolist() == g["batch_sizes"]
+    assert int(bs.sum()) == g["total"]
+
+
+def test_pack_bruteforce_random():
+    rng = np.random.default_rng(40)
+    for trial in range(50):
+        B = int(rng.integers(1, 70))
+        T = int(rng.integers(1, 40))
+        lengths = rng.integers(1, T + 1, B).astype(np.int32)
+        s, u, bs = oracle.pack(lengths, T)
+        expect = sorted(range(B), key=lambda b: (-int(lengths[b]), b))
+        assert s.tolist() == expect
+        assert all(u[s[i]] == i for i in range(B))
+        assert int(bs.sum()) == int(lengths.sum())
+        assert all(bs[t] >= bs[t + 1] for t in range(T - 1))
+        assert bs[0] == B
+        for t in range(T):
+            assert bs[t] == int((lengths > t).sum())
+
+
+def test_pack_rejects_bad_lengths():
+    with pytest.raises(ValueError):
+        oracle.pack(np.array([3, 0, 2], np.int32), 4)
+    with pytest.raises(ValueError):
+        oracle.pack(np.array([3, 5, 2], np.int32), 4)
+
+
+# --------------------------------------------------------------------------- RSSM
+
+def _rssm_torch(w, actions, eps, state0, belief0):
+    """The RSSM prior step assembled from torch float64 modules, as the page lays it out."""
+    T, B, A = actions.shape
+    S = eps.shape[2]
+    Hd = w["W1"].shape[0]
+    RH = w["W_hh"].shape[1]
+    d = lambda a: torch.from_numpy(np.asarray(a)).double()
+    lin1 = torch.nn.Linear(S + A, Hd, dtype=torch.float64)
+    gru = torch.nn.GRUCell(Hd, RH, dtype=torch.float64)
+    lin2 = torch.nn.Linear(RH, Hd, dtype=torch.float64)
+    lin3 = torch.nn.Linear(Hd, 2 * S, dtype=torch.float64)
+    with torch.no_grad():
+        lin1.weight.copy_(d(w["W1"])); lin1.bias.copy_(d(w["b1"]))
+        gru.weight_ih.copy_(d(w["W_ih"])); gru.weight_hh.copy_(d(w["W_hh"]))
+        gru.bias_ih.copy_(d(w["b_ih"])); gru.bias_hh.copy_(d(w["b_hh"]))
+        lin2.weight.copy_(d(w["W2"])); lin2.bias.copy_(d(w["b2"]))
+        lin3.weight.copy_(d(w["W3"])); lin3.bias.copy_(d(w["b3"]))
+        state = torch.zeros(B, S, dtype=torch.float64) if state0 is None else d(state0)
+        belief = torch.zeros(B, RH, dtype=torch.float64) if belief0 is None else d(belief0)
+        outs = []
+        for t in range(T):
+            a = torch.nn.functional.elu(lin1(torch.cat([state, d(actions[t])], dim=-1)))
+            belief = gru(a, belief)
+            p = lin3(torch.nn.functional.elu(lin2(belief)))
+            mean, raw = p[:, :S], p[:, S:]
+            std = torch.nn.functional.softplus(raw) + 0.1
+            state = mean + d(eps[t]) * std
+            outs.append((mean, std, state, belief))
+    return [torch.stack([o[i] for o in outs]).numpy() for i in range(4)]
+
+
+def test_rssm_against_torch_modules():
+    spec = wl.RSSM_B50.scaled(T=6, B=4, state_dim=5, action_dim=3, hidden=7, rnn_hidden=6,
+                              state0_std=1.0, belief0_std=0.5)
+    inp = wl.make_rssm_inputs(spec, seed=3)
+    w = {k: v.numpy() for k, v in inp["weights"].items()}
+    got = oracle.rssm_unroll(w, inp["actions"], inp["eps"], state0=inp["state0"],
+                             belief0=inp["belief0"])
+    ref = _rssm_torch(w, inp["actions"].numpy(), inp["eps"].numpy(), inp["state0"].numpy(),
+                      inp["belief0"].numpy())
+    for g_, r_ in zip(got, ref):
+        np.testing.assert_allclose(g_, r_, rtol=0, atol=1e-12)
+
+
+def test_rssm_zero_weights_golden():
+    g = json.load(open(os.path.join(GOLDEN, "rssm_zero_weights.json")))
+    assert abs(g["std"] - (math.log(2.0) + 0.1)) < 1e-16
+    spec = wl.RSSM_B50.scaled(T=5, B=3)
+    inp = wl.make_rssm_inputs(spec, seed=1)
+    w = {k: np.zeros_like(v.numpy()) for k, v in inp["weights"].items()}
+    means, stds, states, beliefs = oracle.rssm_unroll(w, inp["actions"], inp["eps"])
+    assert np.all(means == g["mean"])
+    np.testing.assert_allclose(stds, g["std"], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(states, g["std"] * inp["eps"].numpy().astype(np.float64),
+                               rtol=0, atol=1e-15)
+    assert np.all(beliefs == g["belief"])
+
+
+def test_rssm_rows_and_permutation():
+    spec = wl.RSSM_B50.scaled(T=4, B=6, hidden=9, rnn_hidden=8, state0_std=1.0,
+                              belief0_std=1.0)
+    inp = wl.make_rssm_inputs(spec, seed=5)
+    w = {k: v.numpy() for k, v in inp["weights"].items()}
+    full = oracle.rssm_unroll(w, inp["actions"], inp["eps"], state0=inp["state0"],
+                              belief0=inp["belief0"])
+    perm = np.array([3, 0, 5, 1, 4, 2])
+    permd = oracle.rssm_unroll(w, inp["actions"].numpy()[:, perm], inp["eps"].numpy()[:, perm],
+                               state0=inp["state0"].numpy()[perm],
+                               belief0=inp["belief0"].numpy()[perm])
+    for f, p in zip(full, permd):
+        np.testing.assert_array_equal(p, f[:, perm])
+    sub = oracle.rssm_unroll(w, inp["actions"], inp["eps"], state0=inp["state0"],
+                             belief0=inp["belief0"], rows=[2, 5])
+    for f, s in zip(full, sub):
+        np.testing.assert_array_equal(s[:, [2, 5]], f[:, [2, 5]])
+
+
+def test_workload_generators_are_seeded():
+    a = wl.make_rnn_inputs(wl.BILSTM_VAR.scaled(T=20, B=5, in_dim=4, hidden=3, varlen=(2, 20)), 0)
+    b = wl.make_rnn_inputs(wl.BILSTM_VAR.scaled(T=20, B=5, in_dim=4, hidden=3, varlen=(2, 20)), 0)
+    assert torch.equal(a["x"], b["x"]) and torch.equal(a["lengths"], b["lengths"])
+    assert int(a["lengths"].min()) >= 2 and int(a["lengths"].max()) <= 20
