@@ -1,0 +1,211 @@
+/*
+ * rcu.h — C ABI of the GB300 recurrent-cell unroll library (librcu.so).
+ *
+ * The library runs the time-unrolled forward pass of stacked LSTM, GRU and
+ * LSTM-with-projection (LSTMP) networks, padded or variable-length, and the
+ * RSSM prior unroll, entirely in its own CUDA kernels (sm_103a).  The caller
+ * supplies device memory and a CUDA stream; nothing here depends on PyTorch.
+ *
+ * Conventions shared by every entry point
+ *  - Return value: RCU_OK (0) or a negative RCU_ERR_* code.  The message of
+ *    the last failure on the calling host thread is returned by
+ *    rcu_last_error().
+ *  - Pointers named as "device" must point to memory the current CUDA device
+ *    can access; all tensors are dense, row-major (C order) and fp32 unless
+ *    stated.  Input and output buffers must not overlap.
+ *  - "stream" is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Work is enqueued asynchronously on it; errors detected on the
+ *    device are reported by rnn_get_status / rssm_get_status.
+ *  - A handle is used from one stream at a time; different handles are
+ *    independent (no global mutable state, cf. the thread-local recurrent
+ *    mode of "[Performance] LSTM/GRU scan: canonical strides + cuDNN
+ *    flat-storage clones + thread-local recurrent mode", pytorch/rl PR 3754).
+ *  - Memory ownership: the caller owns every input/output buffer.  A handle
+ *    owns a private copy of its weights (made by the set_weights calls, so the
+ *    caller may free or reuse its weight tensors at once; cf. the flat-storage
+ *    aliasing fix in pytorch/rl PR 3754) and a workspace that grows on demand
+ *    inside the forward call.
+ */
+#ifndef RCU_H
+#define RCU_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define RCU_API __attribute__((visibility("default")))
+#else
+#define RCU_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct rcu_rnn_s *rcu_rnn_t;
+typedef struct rcu_rssm_s *rcu_rssm_t;
+
+/* Cell kinds; RCU_BIDIR may be OR-ed into the cell argument of rnn_create. */
+#define RCU_LSTM 0
+#define RCU_GRU 1
+#define RCU_BIDIR 0x100
+
+/* Weight storage types.  RCU_BF16: weights rounded to bf16 (nearest-even),
+ * GEMM operands (x, inter-layer outputs, recurrent h, projection input m)
+ * rounded to bf16; accumulation, biases, cell state and all elementwise math
+ * in fp32 (the AMP-style reduced-precision LSTM discussed in "Integrating
+ * CuDNN API for LSTMs with projections", pytorch/pytorch issue 46213). */
+#define RCU_F32 0
+#define RCU_BF16 1
+
+/* Status codes. */
+#define RCU_OK 0
+#define RCU_ERR_INVALID (-1)     /* bad argument: NULL, shape, dims, layer index */
+#define RCU_ERR_UNSUPPORTED (-2) /* e.g. GRU with projection; plan does not fit the GPU */
+#define RCU_ERR_CUDA (-3)        /* CUDA launch or allocation failure */
+#define RCU_ERR_TIMEOUT (-4)     /* a device-side step barrier gave up waiting */
+#define RCU_ERR_LENGTHS (-5)     /* device found a length outside [1, T] */
+#define RCU_ERR_STATE (-6)       /* weights not set for every layer/direction */
+
+/* Attributes for rnn_set_attr / rssm_set_attr. */
+#define RCU_ATTR_BARRIER_TIMEOUT_NS 1 /* bound on any device wait (default 2e9 ns) */
+#define RCU_ATTR_TEST_DROP_ARRIVAL 2  /* testing only: 1 = one CTA never arrives at the
+                                         first step barrier, so the wait must time out */
+#define RCU_ATTR_FORCE_PATH 3         /* 0 = automatic, 1 = portable SIMT kernels only,
+                                         2 = tensor-core (tcgen05) kernels where supported */
+
+/* Message of the last failure on this host thread ("" if none). */
+RCU_API const char *rcu_last_error(void);
+
+/* Library version string. */
+RCU_API const char *rcu_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* Stacked LSTM / GRU / LSTMP                                                 */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Create a network description.
+ *   cell    RCU_LSTM or RCU_GRU, optionally | RCU_BIDIR (two directions per layer).
+ *   layers  >= 1.  Layer l > 0 takes the previous layer's output (forward and
+ *           backward halves concatenated).
+ *   in_dim  input width of layer 0 (>= 1).
+ *   hidden  H, units per direction (>= 1).
+ *   proj    0 = no projection; 0 < proj < hidden = LSTMP with
+ *           h_t = W_hr (o_t * tanh(c_t)) (Sak et al., the cuDNN projection
+ *           named in pytorch/pytorch issue 46213).  proj > 0 with RCU_GRU is
+ *           RCU_ERR_UNSUPPORTED, as the issue asks for RNN/GRU.
+ *   dtype   RCU_F32 or RCU_BF16.
+ * On success *out receives the handle.
+ */
+RCU_API int rnn_create(rcu_rnn_t *out, int cell, int layers, int in_dim, int hidden, int proj, int dtype);
+
+/*
+ * Copy one layer/direction's weights into the handle (PyTorch nn.LSTM/nn.GRU
+ * layout, device pointers, fp32).  Gate row order: LSTM i,f,g,o; GRU r,z,n.
+ *   W_ih [nG*H, in_l]  in_l = in_dim for layer 0, D*Hout after (Hout = proj or H)
+ *   W_hh [nG*H, Hout]
+ *   b_ih, b_hh [nG*H]  NULL means zero ("with and without bias",
+ *                      pytorch/pytorch issue 46213)
+ *   W_hr [proj, H]     required iff proj > 0, else must be NULL
+ * dir is 0, or 1 for the backward direction of a bidirectional network.
+ * The copy is ordered on `stream`; the caller may reuse its buffers once the
+ * stream has passed this call.
+ */
+RCU_API int rnn_set_weights(rcu_rnn_t h, int layer, int dir, const float *W_ih, const float *W_hh,
+                    const float *b_ih, const float *b_hh, const float *W_hr, void *stream);
+
+/*
+ * Forward pass over T steps of B sequences (time-major).
+ *   x        [T, B, in_dim] device.
+ *   lengths  NULL (every row has length T) or device int32 [B] with
+ *            1 <= lengths[b] <= T.  Rows are sorted by length on the device
+ *            and packed (pack/unpack inside the op, "RNN Op Changes",
+ *            apache/mxnet issue 9543); row b only runs steps t < lengths[b];
+ *            the backward direction starts at t = lengths[b]-1.
+ *   h0       [L*D, B, Hout] or NULL (zeros);  c0 [L*D, B, H] or NULL (zeros,
+ *            LSTM only; must be NULL for GRU).
+ *   eps      reserved (no LSTM/GRU cell draws noise); must be NULL.
+ *   y        [T, B, D*Hout] output of the last layer; positions t >= lengths[b]
+ *            are written as 0.
+ *   h_n      [L*D, B, Hout] or NULL; c_n [L*D, B, H] or NULL (LSTM only):
+ *            state after each row's last processed step.
+ * Returns after enqueueing; a device-side failure (length out of range,
+ * barrier timeout) is reported by rnn_get_status.
+ */
+RCU_API int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int32_t *lengths,
+                const float *h0, const float *c0, const float *eps, float *y, float *h_n,
+                float *c_n, void *stream);
+
+/*
+ * Copy the packing metadata of the last rnn_forward (device int32 buffers):
+ *   sorted_idx[B]   original row at sorted position s (length descending,
+ *                   equal lengths in ascending row order),
+ *   unsorted_idx[B] sorted position of original row b,
+ *   batch_sizes[T]  number of rows with length > t.
+ * Any pointer may be NULL.
+ */
+RCU_API int rnn_get_pack(rcu_rnn_t h, int32_t *sorted_idx, int32_t *unsorted_idx, int32_t *batch_sizes,
+                 void *stream);
+
+/* Synchronise `stream` and return the device status of the last forward
+ * (RCU_OK, RCU_ERR_TIMEOUT or RCU_ERR_LENGTHS), then clear it. */
+RCU_API int rnn_get_status(rcu_rnn_t h, void *stream);
+
+/* Set a handle attribute (RCU_ATTR_*). */
+RCU_API int rnn_set_attr(rcu_rnn_t h, int attr, int64_t value);
+
+/* Number of kernel launches the last rnn_forward enqueued. */
+RCU_API int rnn_last_launch_count(rcu_rnn_t h);
+
+/* Free the handle, its weights and workspace (synchronises the device). */
+RCU_API int rnn_destroy(rcu_rnn_t h);
+
+/* ------------------------------------------------------------------------ */
+/* RSSM prior unroll ("[Feature Request] CUDNN version of RSSM",             */
+/* pytorch/rl issue 366, Solution: RSSMPrior and unroll variant 1)           */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Create an RSSM prior: state_dim S, action_dim A, hidden Hd (width of the
+ * action/state projector and of the prior head's hidden layer), rnn_hidden RH
+ * (GRUCell width).  All >= 1 (A >= 0).
+ */
+RCU_API int rssm_create(rcu_rssm_t *out, int state_dim, int action_dim, int hidden, int rnn_hidden);
+
+/*
+ * Copy the prior's weights (device, fp32, PyTorch Linear/GRUCell layout):
+ *   W1 [Hd, S+A], b1 [Hd]            action_state_projector (state columns first)
+ *   W_ih [3RH, Hd], W_hh [3RH, RH], b_ih, b_hh [3RH]   GRUCell (r, z, n)
+ *   W2 [Hd, RH], b2 [Hd]             first Linear of the prior head
+ *   W3 [2S, Hd], b3 [2S]             second Linear (first S rows: mean)
+ * Biases may be NULL (zero).
+ */
+RCU_API int rssm_set_weights(rcu_rssm_t h, const float *W1, const float *b1, const float *W_ih,
+                     const float *W_hh, const float *b_ih, const float *b_hh, const float *W2,
+                     const float *b2, const float *W3, const float *b3, void *stream);
+
+/*
+ * Unroll T steps for B independent rows with given actions.  Per step:
+ *   a = ELU(W1 [state, action_t] + b1); belief = GRUCell(a, belief);
+ *   p = W3 ELU(W2 belief + b2) + b3; mean = p[:S]; std = softplus(p[S:]) + 0.1;
+ *   state = mean + eps_t * std.
+ *   state0 [B, S], belief0 [B, RH]: device or NULL (zeros).
+ *   actions [T, B, A], eps [T, B, S] (the Gaussian noise, supplied by the
+ *   caller so the unroll is deterministic): device.
+ *   means, stds, states [T, B, S]; beliefs [T, B, RH]: device outputs, the
+ *   values after step t's update.
+ */
+RCU_API int rssm_unroll(rcu_rssm_t h, int T, int B, const float *state0, const float *belief0,
+                const float *actions, const float *eps, float *means, float *stds, float *states,
+                float *beliefs, void *stream);
+
+RCU_API int rssm_get_status(rcu_rssm_t h, void *stream);
+RCU_API int rssm_last_launch_count(rcu_rssm_t h);
+RCU_API int rssm_destroy(rcu_rssm_t h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RCU_H */

@@ -1,0 +1,311 @@
+"""Thin ctypes binding of librcu.so (argument marshalling only).
+
+Every function here has the name of the C entry point it calls (see
+include/rcu.h) and only turns torch tensors into device pointers and CUDA
+streams; every step of the computation runs in the library's kernels.  The
+library must have been built (``recurrent_cell_unroll_gb300._build.build()``);
+a missing library raises instead of falling back to anything else.
+
+Inputs are re-materialised when their strides are not the C-canonical ones
+(a tensor of shape [1, 4, 5] with strides (5, 5, 1) passes ``is_contiguous()``
+but is not canonical; see "[Performance] LSTM/GRU scan: canonical strides +
+cuDNN flat-storage clones + thread-local recurrent mode", pytorch/rl PR 3754).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import _build
+
+RCU_LSTM, RCU_GRU, RCU_BIDIR = 0, 1, 0x100
+RCU_F32, RCU_BF16 = 0, 1
+RCU_OK, RCU_ERR_INVALID, RCU_ERR_UNSUPPORTED, RCU_ERR_CUDA = 0, -1, -2, -3
+RCU_ERR_TIMEOUT, RCU_ERR_LENGTHS, RCU_ERR_STATE = -4, -5, -6
+RCU_ATTR_BARRIER_TIMEOUT_NS, RCU_ATTR_TEST_DROP_ARRIVAL, RCU_ATTR_FORCE_PATH = 1, 2, 3
+
+EXPORTED = (
+    "rcu_last_error", "rcu_version", "rnn_create", "rnn_set_weights", "rnn_forward",
+    "rnn_get_pack", "rnn_get_status", "rnn_set_attr", "rnn_last_launch_count", "rnn_destroy",
+    "rssm_create", "rssm_set_weights", "rssm_unroll", "rssm_get_status",
+    "rssm_last_launch_count", "rssm_destroy",
+)
+
+_lib = None
+_lock = threading.Lock()
+
+
+class RcuError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"rcu error {code}: {msg}")
+        self.code = code
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(path: Optional[str] = None):
+    """Load librcu.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or _build.LIB
+        if not os.path.exists(p):
+            raise RuntimeError(f"librcu.so not found at {p}: build it with "
+                               "recurrent_cell_unroll_gb300._build.build()")
+        lib = ctypes.CDLL(p)
+        P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        sig = {
+            "rcu_last_error": (ctypes.c_char_p, []),
+            "rcu_version": (ctypes.c_char_p, []),
+            "rnn_create": (I, [ctypes.POINTER(P), I, I, I, I, I, I]),
+            "rnn_set_weights": (I, [P, I, I, P, P, P, P, P, P]),
+            "rnn_forward": (I, [P, I, I, P, P, P, P, P, P, P, P, P]),
+            "rnn_get_pack": (I, [P, P, P, P, P]),
+            "rnn_get_status": (I, [P, P]),
+            "rnn_set_attr": (I, [P, I, I64]),
+            "rnn_last_launch_count": (I, [P]),
+            "rnn_destroy": (I, [P]),
+            "rssm_create": (I, [ctypes.POINTER(P), I, I, I, I]),
+            "rssm_set_weights": (I, [P] + [P] * 10 + [P]),
+            "rssm_unroll": (I, [P, I, I] + [P] * 8 + [P]),
+            "rssm_get_status": (I, [P, P]),
+            "rssm_last_launch_count": (I, [P]),
+            "rssm_destroy": (I, [P]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(rc: int) -> int:
+    if rc != RCU_OK:
+        raise RcuError(rc, load().rcu_last_error().decode())
+    return rc
+
+
+def canonical_contiguous(t: Optional[torch.Tensor]) -> Optional[torch.Tensor]:
+    """Return t if its strides are the C-canonical ones, else a canonical copy."""
+    if t is None:
+        return None
+    expect, acc = [], 1
+    for n in reversed(t.shape):
+        expect.append(acc)
+        acc *= n
+    if tuple(reversed(expect)) == tuple(t.stride()) and t.storage_offset() >= 0:
+        return t
+    return t.clone(memory_format=torch.contiguous_format)
+
+
+def _dev(t: Optional[torch.Tensor], dtype=torch.float32):
+    if t is None:
+        return None, None
+    if not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    if t.dtype != dtype:
+        raise ValueError(f"expected {dtype}, got {t.dtype}")
+    t = canonical_contiguous(t)
+    return t, ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+# --------------------------------------------------------------------------- C names
+
+def rcu_version() -> str:
+    return load().rcu_version().decode()
+
+
+def rnn_create(cell: int, layers: int, in_dim: int, hidden: int, proj: int = 0,
+               dtype: int = RCU_F32) -> ctypes.c_void_p:
+    h = ctypes.c_void_p()
+    _check(load().rnn_create(ctypes.byref(h), cell, layers, in_dim, hidden, proj, dtype))
+    return h
+
+
+def rnn_set_weights(h, layer: int, direction: int, W_ih, W_hh, b_ih=None, b_hh=None, W_hr=None,
+                    stream=None):
+    keep = [_dev(t) for t in (W_ih, W_hh, b_ih, b_hh, W_hr)]
+    _check(load().rnn_set_weights(h, layer, direction, *[k[1] for k in keep], _stream(stream)))
+
+
+def rnn_forward(h, T: int, B: int, x, lengths, h0, c0, eps, y, h_n, c_n, stream=None):
+    x_, xp = _dev(x)
+    l_, lp = _dev(lengths, torch.int32)
+    h0_, h0p = _dev(h0)
+    c0_, c0p = _dev(c0)
+    e_, ep = _dev(eps)
+    for out in (y, h_n, c_n):
+        if out is not None and not out.is_contiguous():
+            raise ValueError("outputs must be contiguous")
+    _, yp = _dev(y)
+    _, hnp = _dev(h_n)
+    _, cnp = _dev(c_n)
+    _check(load().rnn_forward(h, T, B, xp, lp, h0p, c0p, ep, yp, hnp, cnp, _stream(stream)))
+
+
+def rnn_get_pack(h, sorted_idx, unsorted_idx, batch_sizes, stream=None):
+    _check(load().rnn_get_pack(h, *[_dev(t, torch.int32)[1] for t in
+                                   (sorted_idx, unsorted_idx, batch_sizes)], _stream(stream)))
+
+
+def rnn_get_status(h, stream=None) -> int:
+    """Synchronise and return the device status code (0 = ok); does not raise."""
+    return load().rnn_get_status(h, _stream(stream))
+
+
+def rnn_set_attr(h, attr: int, value: int):
+    _check(load().rnn_set_attr(h, attr, value))
+
+
+def rnn_last_launch_count(h) -> int:
+    return load().rnn_last_launch_count(h)
+
+
+def rnn_destroy(h):
+    if h:
+        load().rnn_destroy(h)
+
+
+def rssm_create(state_dim: int, action_dim: int, hidden: int, rnn_hidden: int):
+    h = ctypes.c_void_p()
+    _check(load().rssm_create(ctypes.byref(h), state_dim, action_dim, hidden, rnn_hidden))
+    return h
+
+
+def rssm_set_weights(h, W1, b1, W_ih, W_hh, b_ih, b_hh, W2, b2, W3, b3, stream=None):
+    keep = [_dev(t) for t in (W1, b1, W_ih, W_hh, b_ih, b_hh, W2, b2, W3, b3)]
+    _check(load().rssm_set_weights(h, *[k[1] for k in keep], _stream(stream)))
+
+
+def rssm_unroll(h, T: int, B: int, state0, belief0, actions, eps, means, stds, states, beliefs,
+                stream=None):
+    ins = [_dev(t) for t in (state0, belief0, actions, eps)]
+    outs = [_dev(t) for t in (means, stds, states, beliefs)]
+    _check(load().rssm_unroll(h, T, B, *[k[1] for k in ins], *[k[1] for k in outs],
+                              _stream(stream)))
+
+
+def rssm_get_status(h, stream=None) -> int:
+    return load().rssm_get_status(h, _stream(stream))
+
+
+def rssm_last_launch_count(h) -> int:
+    return load().rssm_last_launch_count(h)
+
+
+def rssm_destroy(h):
+    if h:
+        load().rssm_destroy(h)
+
+
+# --------------------------------------------------------------------------- convenience wrappers
+
+class RNN:
+    """Owns an rnn handle; weights from the seeded-workload dict layout."""
+
+    def __init__(self, cell: str, layers: int, in_dim: int, hidden: int, proj: int = 0,
+                 bidirectional: bool = False, dtype: str = "f32"):
+        c = RCU_LSTM if cell == "lstm" else RCU_GRU
+        if bidirectional:
+            c |= RCU_BIDIR
+        self.cell, self.layers, self.hidden, self.proj = cell, layers, hidden, proj
+        self.D = 2 if bidirectional else 1
+        self.Hout = proj if proj > 0 else hidden
+        self.h = rnn_create(c, layers, in_dim, hidden, proj, RCU_BF16 if dtype == "bf16" else RCU_F32)
+
+    @classmethod
+    def from_spec(cls, spec):
+        return cls(spec.cell, spec.layers, spec.in_dim, spec.hidden, spec.proj, spec.bidir, spec.dtype)
+
+    def set_weights(self, weights, device="cuda", stream=None):
+        for i, w in enumerate(weights):
+            layer, d = divmod(i, self.D)
+            t = {k: (None if v is None else v.to(device=device, dtype=torch.float32))
+                 for k, v in w.items()}
+            rnn_set_weights(self.h, layer, d, t["w_ih"], t["w_hh"], t.get("b_ih"), t.get("b_hh"),
+                            t.get("w_hr"), stream)
+
+    def forward(self, x, lengths=None, h0=None, c0=None, out=None, stream=None):
+        T, B, _ = x.shape
+        dev = x.device
+        y = out if out is not None else torch.empty((T, B, self.D * self.Hout), device=dev)
+        hn = torch.empty((self.layers * self.D, B, self.Hout), device=dev)
+        cn = torch.empty((self.layers * self.D, B, self.hidden), device=dev) \
+            if self.cell == "lstm" else None
+        rnn_forward(self.h, T, B, x, lengths, h0, c0, None, y, hn, cn, stream)
+        return y, hn, cn
+
+    def status(self, stream=None) -> int:
+        return rnn_get_status(self.h, stream)
+
+    def set_attr(self, attr, value):
+        rnn_set_attr(self.h, attr, value)
+
+    def launch_count(self) -> int:
+        return rnn_last_launch_count(self.h)
+
+    def close(self):
+        if self.h:
+            rnn_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class RSSM:
+    """Owns an rssm handle."""
+
+    def __init__(self, state_dim: int, action_dim: int, hidden: int, rnn_hidden: int):
+        self.S, self.A, self.Hd, self.RH = state_dim, action_dim, hidden, rnn_hidden
+        self.h = rssm_create(state_dim, action_dim, hidden, rnn_hidden)
+
+    def set_weights(self, w, device="cuda", stream=None):
+        t = {k: (None if v is None else v.to(device=device, dtype=torch.float32))
+             for k, v in w.items()}
+        rssm_set_weights(self.h, t["W1"], t.get("b1"), t["W_ih"], t["W_hh"], t.get("b_ih"),
+                         t.get("b_hh"), t["W2"], t.get("b2"), t["W3"], t.get("b3"), stream)
+
+    def unroll(self, actions, eps, state0=None, belief0=None, stream=None):
+        T, B, _ = eps.shape
+        dev = eps.device
+        means = torch.empty((T, B, self.S), device=dev)
+        stds = torch.empty_like(means)
+        states = torch.empty_like(means)
+        beliefs = torch.empty((T, B, self.RH), device=dev)
+        rssm_unroll(self.h, T, B, state0, belief0, actions, eps, means, stds, states, beliefs,
+                    stream)
+        return means, stds, states, beliefs
+
+    def launch_count(self) -> int:
+        return rssm_last_launch_count(self.h)
+
+    def close(self):
+        if self.h:
+            rssm_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,623 @@
+// Host side of the C ABI declared in include/rcu.h: handles, weight packing,
+// workspace, planning and launch sequencing.  Every step of the forward pass
+// runs in this library's kernels; nothing falls back to the host.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "rcu.h"
+#include "common.cuh"
+#include "internal.h"
+#include "tc.h"
+
+using namespace rcu;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+#define CU(expr)                                                                        \
+  do {                                                                                  \
+    cudaError_t e_ = (expr);                                                            \
+    if (e_ != cudaSuccess)                                                              \
+      return fail(RCU_ERR_CUDA, "%s failed: %s (%s:%d)", #expr, cudaGetErrorString(e_), \
+                  __FILE__, __LINE__);                                                  \
+  } while (0)
+
+// fp32 -> bf16 bits, round to nearest even (NaN kept quiet).
+uint16_t f2bf(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  if ((u & 0x7f800000u) == 0x7f800000u) return (uint16_t)((u >> 16) | ((u & 0x7fffffu) ? 0x40u : 0u));
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+int device_sm_count(int *dev) {
+  cudaGetDevice(dev);
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, *dev);
+  return n > 0 ? n : 1;
+}
+
+// Copy a device fp32 tensor to the host (synchronous on `s`).
+cudaError_t fetch(std::vector<float> &dst, const float *src, size_t n, cudaStream_t s) {
+  dst.assign(n, 0.f);
+  if (!src || n == 0) return cudaSuccess;
+  cudaError_t e = cudaMemcpyAsync(dst.data(), src, n * sizeof(float), cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(s);
+}
+
+struct DevBuf {
+  void *p = nullptr;
+  size_t n = 0;
+  ~DevBuf() { if (p) cudaFree(p); }
+  cudaError_t ensure(size_t bytes) {
+    if (bytes <= n) return cudaSuccess;
+    if (p) { cudaFree(p); p = nullptr; n = 0; }
+    cudaError_t e = cudaMalloc(&p, bytes);
+    if (e == cudaSuccess) n = bytes;
+    return e;
+  }
+  // upload host bytes (synchronous)
+  cudaError_t upload(const void *src, size_t bytes) {
+    cudaError_t e = ensure(bytes);
+    if (e != cudaSuccess) return e;
+    return cudaMemcpy(p, src, bytes, cudaMemcpyHostToDevice);
+  }
+};
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// network handle
+
+struct LayerDirW {
+  DevBuf whh, whr, bhn;  // SIMT-packed recurrent weights, projection, GRU b_hn
+  DevBuf tc_whh;         // tensor-core packed recurrent weights (bf16 path)
+  bool set = false;
+};
+
+struct rcu_rnn_s {
+  int cell, layers, D, in_dim, H, P, Hout, nG, dtype;
+  int device, nsm;
+  // SIMT plan
+  int U, NU, Rp, Kp, Hp, Pc, Pcp, NP;
+  std::vector<int> in_l;         // GEMM K per layer
+  std::vector<DevBuf> wih;       // [D*nG*H][ldk] per layer (dtype), ldk = round_up(in_l, 8)
+  std::vector<DevBuf> gbias;     // [D*nG*H] fp32 per layer
+  std::vector<std::vector<float>> host_bias; // staging: per layer, filled by set_weights
+  std::vector<LayerDirW> lw;     // layers*D
+  // workspace
+  DevBuf ctl;   // err word + counters
+  DevBuf ws;
+  Meta meta{};
+  int ws_T = -1, ws_B = -1;
+  int last_T = -1, last_B = -1;
+  char *xp = nullptr, *g = nullptr, *ymid = nullptr, *hx = nullptr, *mx = nullptr;
+  float *hst = nullptr, *cst = nullptr;
+  int64_t timeout_ns = 2000000000LL;
+  int drop_arrival = 0;
+  int force_path = 0;
+  int launches = 0;
+  bool used_tc_gemm = false, used_tc_rec = false;
+};
+
+static size_t esize(int dtype) { return dtype == RCU_BF16 ? 2 : 4; }
+// control block: error word at 0, then 4 barrier counters per layer from byte 64
+static size_t ctl_bytes(int layers) { return 64 + 16 * (size_t)layers + 64; }
+
+extern "C" const char *rcu_last_error(void) { return g_last_error.c_str(); }
+extern "C" const char *rcu_version(void) { return "rcu 0.1 (sm_103a)"; }
+
+static void plan_simt(rcu_rnn_s *h) {
+  const int budget = std::max(1, h->nsm / h->D);
+  int U = ceil_div(h->H, budget);
+  h->U = U;
+  h->NU = ceil_div(h->H, U);
+  h->Rp = round_up(h->nG * U, 4);
+  h->Kp = round_up(h->Hout, 8);
+  h->Hp = round_up(h->H, 8);
+  if (h->P > 0) {
+    h->Pc = ceil_div(h->P, h->NU);
+    h->Pcp = round_up(h->Pc, 4);
+    h->NP = ceil_div(h->P, h->Pc);
+  } else {
+    h->Pc = h->Pcp = h->NP = 0;
+  }
+}
+
+extern "C" int rnn_create(rcu_rnn_t *out, int cell, int layers, int in_dim, int hidden, int proj,
+                          int dtype) {
+  if (!out) return fail(RCU_ERR_INVALID, "rnn_create: out is NULL");
+  *out = nullptr;
+  const int base = cell & 0xff;
+  const bool bidir = (cell & RCU_BIDIR) != 0;
+  if ((cell & ~(0xff | RCU_BIDIR)) != 0 || (base != RCU_LSTM && base != RCU_GRU))
+    return fail(RCU_ERR_INVALID, "rnn_create: unknown cell %d", cell);
+  if (layers < 1 || in_dim < 1 || hidden < 1 || proj < 0)
+    return fail(RCU_ERR_INVALID, "rnn_create: layers, in_dim, hidden must be >= 1, proj >= 0");
+  if (proj > 0 && base != RCU_LSTM)
+    return fail(RCU_ERR_UNSUPPORTED, "rnn_create: projection is only defined for LSTM");
+  if (proj >= hidden && proj > 0)
+    return fail(RCU_ERR_INVALID, "rnn_create: proj must be smaller than hidden");
+  if (dtype != RCU_F32 && dtype != RCU_BF16)
+    return fail(RCU_ERR_INVALID, "rnn_create: unknown dtype %d", dtype);
+  auto *h = new rcu_rnn_s();
+  h->cell = base;
+  h->layers = layers;
+  h->D = bidir ? 2 : 1;
+  h->in_dim = in_dim;
+  h->H = hidden;
+  h->P = proj;
+  h->Hout = proj > 0 ? proj : hidden;
+  h->nG = base == RCU_LSTM ? 4 : 3;
+  h->dtype = dtype;
+  h->nsm = device_sm_count(&h->device);
+  plan_simt(h);
+  h->in_l.resize(layers);
+  h->wih.resize(layers);
+  h->gbias.resize(layers);
+  h->host_bias.resize(layers);
+  h->lw.resize((size_t)layers * h->D);
+  for (int l = 0; l < layers; ++l) {
+    h->in_l[l] = l == 0 ? in_dim : h->D * h->Hout;
+    h->host_bias[l].assign((size_t)h->D * h->nG * h->H, 0.f);
+  }
+  cudaError_t e = h->ctl.ensure(ctl_bytes(layers));
+  if (e != cudaSuccess) {
+    delete h;
+    return fail(RCU_ERR_CUDA, "rnn_create: cudaMalloc failed: %s", cudaGetErrorString(e));
+  }
+  cudaMemset(h->ctl.p, 0, ctl_bytes(layers));
+  *out = h;
+  return RCU_OK;
+}
+
+extern "C" int rnn_set_attr(rcu_rnn_t h, int attr, int64_t value) {
+  if (!h) return fail(RCU_ERR_INVALID, "rnn_set_attr: NULL handle");
+  switch (attr) {
+    case RCU_ATTR_BARRIER_TIMEOUT_NS:
+      if (value <= 0) return fail(RCU_ERR_INVALID, "timeout must be > 0");
+      h->timeout_ns = value;
+      return RCU_OK;
+    case RCU_ATTR_TEST_DROP_ARRIVAL: h->drop_arrival = value != 0; return RCU_OK;
+    case RCU_ATTR_FORCE_PATH:
+      if (value < 0 || value > 2) return fail(RCU_ERR_INVALID, "force_path must be 0, 1 or 2");
+      h->force_path = (int)value;
+      return RCU_OK;
+    default: return fail(RCU_ERR_INVALID, "rnn_set_attr: unknown attribute %d", attr);
+  }
+}
+
+extern "C" int rnn_set_weights(rcu_rnn_t h, int layer, int dir, const float *W_ih,
+                               const float *W_hh, const float *b_ih, const float *b_hh,
+                               const float *W_hr, void *stream) {
+  if (!h) return fail(RCU_ERR_INVALID, "rnn_set_weights: NULL handle");
+  if (layer < 0 || layer >= h->layers || dir < 0 || dir >= h->D)
+    return fail(RCU_ERR_INVALID, "rnn_set_weights: layer %d / dir %d out of range", layer, dir);
+  if (!W_ih || !W_hh) return fail(RCU_ERR_INVALID, "rnn_set_weights: W_ih and W_hh are required");
+  if ((h->P > 0) != (W_hr != nullptr))
+    return fail(RCU_ERR_INVALID, "rnn_set_weights: W_hr must be given iff proj > 0");
+  cudaStream_t s = (cudaStream_t)stream;
+  const int H = h->H, nG = h->nG, Hout = h->Hout, P = h->P, D = h->D;
+  const int in = h->in_l[layer];
+  const int ldk = round_up(in, 8);
+  std::vector<float> wih, whh, bih, bhh, whr;
+  CU(fetch(wih, W_ih, (size_t)nG * H * in, s));
+  CU(fetch(whh, W_hh, (size_t)nG * H * Hout, s));
+  CU(fetch(bih, b_ih, (size_t)nG * H, s));
+  CU(fetch(bhh, b_hh, (size_t)nG * H, s));
+  if (P > 0) CU(fetch(whr, W_hr, (size_t)P * H, s));
+  const bool bf = h->dtype == RCU_BF16;
+  const size_t es = esize(h->dtype);
+  auto put = [&](std::vector<unsigned char> &buf, size_t idx, float v) {
+    if (bf) {
+      uint16_t b = f2bf(v);
+      std::memcpy(&buf[idx * 2], &b, 2);
+    } else {
+      std::memcpy(&buf[idx * 4], &v, 4);
+    }
+  };
+
+  // --- GEMM weights: rows [dir*nG*H, +nG*H) of the layer's [D*nG*H][ldk] matrix
+  DevBuf &gw = h->wih[layer];
+  const size_t gw_bytes = (size_t)D * nG * H * ldk * es;
+  if (gw.n < gw_bytes) {
+    CU(gw.ensure(gw_bytes));
+    CU(cudaMemset(gw.p, 0, gw_bytes));
+  }
+  {
+    std::vector<unsigned char> buf((size_t)nG * H * ldk * es, 0);
+    for (int r = 0; r < nG * H; ++r)
+      for (int k = 0; k < in; ++k) put(buf, (size_t)r * ldk + k, wih[(size_t)r * in + k]);
+    CU(cudaMemcpy((char *)gw.p + (size_t)dir * nG * H * ldk * es, buf.data(), buf.size(),
+                  cudaMemcpyHostToDevice));
+  }
+  // --- GEMM bias: LSTM b_ih + b_hh; GRU r,z: b_ih + b_hh, n: b_ih (b_hn stays with r*(.))
+  {
+    std::vector<float> &hb = h->host_bias[layer];
+    for (int r = 0; r < nG * H; ++r) {
+      const bool gru_n = h->cell == RCU_GRU && r >= 2 * H;
+      hb[(size_t)dir * nG * H + r] = bih[r] + (gru_n ? 0.f : bhh[r]);
+    }
+    CU(h->gbias[layer].upload(hb.data(), hb.size() * sizeof(float)));
+  }
+  LayerDirW &lw = h->lw[(size_t)layer * D + dir];
+  // --- recurrent weights, SIMT layout [NU][Kp][Rp]: row g*U + j = gate g of unit ug*U + j
+  {
+    const int U = h->U, NU = h->NU, Kp = h->Kp, Rp = h->Rp;
+    std::vector<unsigned char> buf((size_t)NU * Kp * Rp * es, 0);
+    for (int ug = 0; ug < NU; ++ug)
+      for (int g = 0; g < nG; ++g)
+        for (int j = 0; j < U; ++j) {
+          const int u = ug * U + j;
+          if (u >= H) continue;
+          for (int k = 0; k < Hout; ++k)
+            put(buf, ((size_t)ug * Kp + k) * Rp + g * U + j, whh[(size_t)(g * H + u) * Hout + k]);
+        }
+    CU(lw.whh.upload(buf.data(), buf.size()));
+  }
+  if (P > 0) {  // projection rows, layout [NP][Hp][Pcp]
+    const int Pc = h->Pc, NP = h->NP, Hp = h->Hp, Pcp = h->Pcp;
+    std::vector<unsigned char> buf((size_t)NP * Hp * Pcp * es, 0);
+    for (int pg = 0; pg < NP; ++pg)
+      for (int j = 0; j < Pc; ++j) {
+        const int q = pg * Pc + j;
+        if (q >= P) continue;
+        for (int k = 0; k < H; ++k) put(buf, ((size_t)pg * Hp + k) * Pcp + j, whr[(size_t)q * H + k]);
+      }
+    CU(lw.whr.upload(buf.data(), buf.size()));
+  }
+  if (h->cell == RCU_GRU) {
+    std::vector<float> bn(H);
+    for (int j = 0; j < H; ++j) bn[j] = bhh[2 * H + j];
+    CU(lw.bhn.upload(bn.data(), bn.size() * sizeof(float)));
+  }
+  // --- tensor-core layout (bf16 path only)
+  if (bf && tc_rec_supported(h->cell, H, Hout, P, h->nsm)) {
+    std::vector<uint16_t> packed;
+    tc_pack_whh(h->cell, H, Hout, whh.data(), packed, f2bf);
+    CU(lw.tc_whh.upload(packed.data(), packed.size() * 2));
+  }
+  lw.set = true;
+  return RCU_OK;
+}
+
+// Workspace for T, B (grows on demand).
+static int ensure_ws(rcu_rnn_s *h, int T, int B) {
+  if (T <= h->ws_T && B <= h->ws_B && h->ws.p) {
+    // reuse; pointers were laid out for (ws_T, ws_B) and stay valid for smaller shapes
+  } else {
+    const int Tm = std::max(T, h->ws_T), Bm = std::max(B, h->ws_B);
+    const size_t M = (size_t)Tm * Bm;
+    const size_t es = esize(h->dtype);
+    const int N = h->D * h->nG * h->H;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t r = off; off = round_up_sz(off + bytes, 256); return r; };
+    const size_t o_meta = take(((size_t)3 * Bm + 2 * Tm + 1) * 4);
+    const size_t o_xp = take(M * round_up(h->in_dim, 8) * es);
+    const size_t o_g = take(M * N * 4);
+    const size_t o_ymid = h->layers > 1 ? take(M * h->D * h->Hout * es) : 0;
+    const size_t o_hx = take((size_t)h->D * 2 * Bm * h->Kp * es);
+    const size_t o_mx = take((size_t)h->D * Bm * h->Hp * es);
+    const size_t o_hst = take((size_t)h->D * Bm * h->Hout * 4);
+    const size_t o_cst = take((size_t)h->D * Bm * h->H * 4);
+    cudaError_t e = h->ws.ensure(off);
+    if (e != cudaSuccess)
+      return fail(RCU_ERR_CUDA, "workspace allocation of %zu bytes failed: %s", off,
+                  cudaGetErrorString(e));
+    char *base = (char *)h->ws.p;
+    int32_t *mi = (int32_t *)(base + o_meta);
+    h->meta.sorted_idx = mi;
+    h->meta.unsorted_idx = mi + Bm;
+    h->meta.lens_sorted = mi + 2 * Bm;
+    h->meta.batch_sizes = mi + 3 * Bm;
+    h->meta.step_off = mi + 3 * Bm + Tm;
+    h->xp = base + o_xp;
+    h->g = base + o_g;
+    h->ymid = h->layers > 1 ? base + o_ymid : nullptr;
+    h->hx = base + o_hx;
+    h->mx = base + o_mx;
+    h->hst = (float *)(base + o_hst);
+    h->cst = (float *)(base + o_cst);
+    h->ws_T = Tm;
+    h->ws_B = Bm;
+  }
+  return RCU_OK;
+}
+
+extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int32_t *lengths,
+                           const float *h0, const float *c0, const float *eps, float *y,
+                           float *h_n, float *c_n, void *stream) {
+  if (!h) return fail(RCU_ERR_INVALID, "rnn_forward: NULL handle");
+  h->launches = 0;
+  if (T < 0 || B < 0) return fail(RCU_ERR_INVALID, "rnn_forward: T and B must be >= 0");
+  if (eps) return fail(RCU_ERR_INVALID, "rnn_forward: eps is reserved and must be NULL");
+  if (h->cell == RCU_GRU && (c0 || c_n))
+    return fail(RCU_ERR_INVALID, "rnn_forward: c0/c_n are LSTM-only");
+  for (auto &w : h->lw)
+    if (!w.set) return fail(RCU_ERR_STATE, "rnn_forward: weights missing for some layer/direction");
+  if (T == 0 || B == 0) return RCU_OK;
+  if (!x || !y) return fail(RCU_ERR_INVALID, "rnn_forward: x and y are required");
+  if ((size_t)T * B > (size_t)INT32_MAX / 4)
+    return fail(RCU_ERR_UNSUPPORTED, "rnn_forward: T*B too large");
+  if (int rc = ensure_ws(h, T, B)) return rc;
+  h->last_T = T;
+  h->last_B = B;
+  cudaStream_t s = (cudaStream_t)stream;
+  const bool bf = h->dtype == RCU_BF16;
+  const size_t es = esize(h->dtype);
+  const int D = h->D, H = h->H, Hout = h->Hout, nG = h->nG;
+  const int N = D * nG * H;
+  const bool varlen = lengths != nullptr;
+  int *err = (int *)h->ctl.p;
+  unsigned *ctr = (unsigned *)((char *)h->ctl.p + 64);
+
+  CU(cudaMemsetAsync(h->ctl.p, 0, ctl_bytes(h->layers), s));
+  CU(cudaMemsetAsync(h->hx, 0, (size_t)D * 2 * B * h->Kp * es, s));
+  if (h->P > 0) CU(cudaMemsetAsync(h->mx, 0, (size_t)D * B * h->Hp * es, s));
+  CU(launch_meta(lengths, B, T, h->meta, err, s));
+  h->launches++;
+  if (varlen) {
+    CU(launch_zero_tail(y, lengths, T, B, D * Hout, err, s));
+    h->launches++;
+  }
+
+  // layer-0 GEMM operand
+  const void *X = x;
+  int ldx = h->in_dim;
+  const int32_t *M_dev = varlen ? h->meta.step_off + T : nullptr;
+  const int Mmax = T * B;
+  if (varlen || bf) {
+    ldx = round_up(h->in_dim, 8);
+    if (bf)
+      CU(launch_pack_rows<__nv_bfloat16>(x, T, B, h->in_dim, h->meta, (__nv_bfloat16 *)h->xp,
+                                         ldx, s));
+    else
+      CU(launch_pack_rows<float>(x, T, B, h->in_dim, h->meta, (float *)h->xp, ldx, s));
+    h->launches++;
+    X = h->xp;
+  }
+  h->used_tc_gemm = h->used_tc_rec = false;
+  for (int l = 0; l < h->layers; ++l) {
+    const int K = h->in_l[l];
+    const int ldw = round_up(K, 8);
+    float *G = (float *)h->g;
+    bool done = false;
+    if (bf && h->force_path != 1 && tc_gemm_supported(K, N)) {
+      cudaError_t e = launch_tc_gemm((const __nv_bfloat16 *)X, ldx, (const __nv_bfloat16 *)h->wih[l].p,
+                                     ldw, (const float *)h->gbias[l].p, G, N, Mmax, M_dev, N, K,
+                                     h->nsm, s);
+      if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "tc gemm: %s", cudaGetErrorString(e));
+      done = true;
+      h->used_tc_gemm = true;
+    }
+    if (!done) {
+      cudaError_t e = bf ? launch_gemm_simt<__nv_bfloat16, __nv_bfloat16>(
+                               (const __nv_bfloat16 *)X, ldx, (const __nv_bfloat16 *)h->wih[l].p,
+                               ldw, (const float *)h->gbias[l].p, G, N, Mmax, M_dev, N, K, s)
+                         : launch_gemm_simt<float, float>((const float *)X, ldx,
+                                                          (const float *)h->wih[l].p, ldw,
+                                                          (const float *)h->gbias[l].p, G, N,
+                                                          Mmax, M_dev, N, K, s);
+      if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "gemm: %s", cudaGetErrorString(e));
+    }
+    h->launches++;
+
+    const bool last = l == h->layers - 1;
+    RecParams p{};
+    p.T = T; p.B = B; p.H = H; p.Hout = Hout; p.Kp = h->Kp; p.Hp = h->Hp; p.nG = nG; p.D = D;
+    p.cell = h->cell; p.proj = h->P;
+    p.U = h->U; p.NU = h->NU; p.Rp = h->Rp;
+    p.Pc = h->Pc; p.Pcp = h->Pcp; p.NP = h->NP;
+    p.meta = h->meta;
+    p.G = G; p.ldG = N;
+    for (int d = 0; d < D; ++d) {
+      LayerDirW &lw = h->lw[(size_t)l * D + d];
+      p.Whh[d] = lw.whh.p;
+      p.Whr[d] = lw.whr.p;
+      p.bhn[d] = (const float *)lw.bhn.p;
+    }
+    p.h0 = h0 ? h0 + (size_t)l * D * B * Hout : nullptr;
+    p.c0 = c0 ? c0 + (size_t)l * D * B * H : nullptr;
+    p.h_n = h_n ? h_n + (size_t)l * D * B * Hout : nullptr;
+    p.c_n = c_n ? c_n + (size_t)l * D * B * H : nullptr;
+    p.y = last ? y : nullptr;
+    p.ymid = last ? nullptr : h->ymid;
+    p.hx = h->hx; p.mx = h->mx; p.hst = h->hst; p.cst = h->cst;
+    p.ctr = ctr + 4 * l;  // fresh counters per layer (zeroed above)
+    p.err = err;
+    p.timeout_ns = (uint64_t)h->timeout_ns;
+    p.drop_arrival = h->drop_arrival && l == 0;
+    bool rec_done = false;
+    if (bf && h->force_path != 1 && tc_rec_supported(h->cell, H, Hout, h->P, h->nsm) &&
+        h->lw[(size_t)l * D].tc_whh.p) {
+      TcRecParams tp;
+      tp.base = p;
+      for (int d = 0; d < D; ++d) tp.Wtc[d] = h->lw[(size_t)l * D + d].tc_whh.p;
+      cudaError_t e = launch_tc_recurrent(tp, h->nsm, s);
+      if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "tc recurrent: %s", cudaGetErrorString(e));
+      rec_done = true;
+      h->used_tc_rec = true;
+    }
+    if (!rec_done) {
+      // shrink the batch chunk until the shared-memory plan fits
+      int CB = std::min(32, round_up(std::max(B, 1), 4));
+      for (;;) {
+        p.CB = CB;
+        const bool tiles_ok = (CB / 4) * (p.Rp / 4) <= 256 && (h->P == 0 || (CB / 4) * (p.Pcp / 4) <= 256);
+        if (tiles_ok && recurrent_simt_smem(p, bf) <= 227 * 1024) break;
+        if (CB <= 4)
+          return fail(RCU_ERR_UNSUPPORTED, "recurrent kernel: resident weights do not fit");
+        CB -= 4;
+      }
+      cudaError_t e = launch_recurrent_simt(p, bf, h->nsm, s);
+      if (e != cudaSuccess)
+        return fail(RCU_ERR_CUDA, "recurrent kernel launch: %s", cudaGetErrorString(e));
+    }
+    h->launches++;
+    // next layer reads this layer's packed output
+    X = h->ymid;
+    ldx = D * Hout;
+  }
+  (void)es;
+  return RCU_OK;
+}
+
+extern "C" int rnn_get_pack(rcu_rnn_t h, int32_t *sorted_idx, int32_t *unsorted_idx,
+                            int32_t *batch_sizes, void *stream) {
+  if (!h) return fail(RCU_ERR_INVALID, "rnn_get_pack: NULL handle");
+  if (h->last_B < 0) return fail(RCU_ERR_STATE, "rnn_get_pack: no forward has run");
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t nb = (size_t)h->last_B * 4, nt = (size_t)h->last_T * 4;
+  if (sorted_idx)
+    CU(cudaMemcpyAsync(sorted_idx, h->meta.sorted_idx, nb, cudaMemcpyDeviceToDevice, s));
+  if (unsorted_idx)
+    CU(cudaMemcpyAsync(unsorted_idx, h->meta.unsorted_idx, nb, cudaMemcpyDeviceToDevice, s));
+  if (batch_sizes)
+    CU(cudaMemcpyAsync(batch_sizes, h->meta.batch_sizes, nt, cudaMemcpyDeviceToDevice, s));
+  return RCU_OK;
+}
+
+static int status_from_dev(int v) {
+  switch (v) {
+    case DEV_OK: return RCU_OK;
+    case DEV_TIMEOUT: return fail(RCU_ERR_TIMEOUT, "device step barrier timed out");
+    case DEV_LENGTHS: return fail(RCU_ERR_LENGTHS, "a length was outside [1, T]");
+    default: return fail(RCU_ERR_CUDA, "unknown device status %d", v);
+  }
+}
+
+extern "C" int rnn_get_status(rcu_rnn_t h, void *stream) {
+  if (!h) return fail(RCU_ERR_INVALID, "rnn_get_status: NULL handle");
+  cudaStream_t s = (cudaStream_t)stream;
+  CU(cudaStreamSynchronize(s));
+  CU(cudaGetLastError());
+  int v = 0;
+  CU(cudaMemcpy(&v, h->ctl.p, sizeof v, cudaMemcpyDeviceToHost));
+  CU(cudaMemset(h->ctl.p, 0, sizeof v));
+  return status_from_dev(v);
+}
+
+extern "C" int rnn_last_launch_count(rcu_rnn_t h) { return h ? h->launches : -1; }
+
+extern "C" int rnn_destroy(rcu_rnn_t h) {
+  if (!h) return RCU_OK;
+  cudaDeviceSynchronize();
+  delete h;
+  return RCU_OK;
+}
+
+// ---------------------------------------------------------------------------
+// RSSM handle
+
+struct rcu_rssm_s {
+  int S, A, Hd, RH;
+  int device, nsm;
+  DevBuf W1, b1, Wih, Whh, bih, bhh, W2, b2, W3, b3;
+  bool set = false;
+  int launches = 0;
+  DevBuf ctl;
+};
+
+extern "C" int rssm_create(rcu_rssm_t *out, int state_dim, int action_dim, int hidden,
+                           int rnn_hidden) {
+  if (!out) return fail(RCU_ERR_INVALID, "rssm_create: out is NULL");
+  *out = nullptr;
+  if (state_dim < 1 || action_dim < 0 || hidden < 1 || rnn_hidden < 1)
+    return fail(RCU_ERR_INVALID, "rssm_create: dims must be >= 1 (action_dim >= 0)");
+  if (!rssm_supported(state_dim, action_dim, hidden, rnn_hidden))
+    return fail(RCU_ERR_UNSUPPORTED, "rssm_create: weights do not fit one cluster's shared memory");
+  auto *h = new rcu_rssm_s();
+  h->S = state_dim; h->A = action_dim; h->Hd = hidden; h->RH = rnn_hidden;
+  h->nsm = device_sm_count(&h->device);
+  if (h->ctl.ensure(256) != cudaSuccess) { delete h; return fail(RCU_ERR_CUDA, "rssm_create: alloc"); }
+  cudaMemset(h->ctl.p, 0, 256);
+  *out = h;
+  return RCU_OK;
+}
+
+extern "C" int rssm_set_weights(rcu_rssm_t h, const float *W1, const float *b1, const float *W_ih,
+                                const float *W_hh, const float *b_ih, const float *b_hh,
+                                const float *W2, const float *b2, const float *W3, const float *b3,
+                                void *stream) {
+  if (!h) return fail(RCU_ERR_INVALID, "rssm_set_weights: NULL handle");
+  if (!W1 || !W_ih || !W_hh || !W2 || !W3)
+    return fail(RCU_ERR_INVALID, "rssm_set_weights: weight matrices are required");
+  cudaStream_t s = (cudaStream_t)stream;
+  const int S = h->S, A = h->A, Hd = h->Hd, RH = h->RH;
+  struct Item { DevBuf *dst; const float *src; size_t n; };
+  Item items[] = {{&h->W1, W1, (size_t)Hd * (S + A)}, {&h->b1, b1, (size_t)Hd},
+                  {&h->Wih, W_ih, (size_t)3 * RH * Hd}, {&h->Whh, W_hh, (size_t)3 * RH * RH},
+                  {&h->bih, b_ih, (size_t)3 * RH}, {&h->bhh, b_hh, (size_t)3 * RH},
+                  {&h->W2, W2, (size_t)Hd * RH}, {&h->b2, b2, (size_t)Hd},
+                  {&h->W3, W3, (size_t)2 * S * Hd}, {&h->b3, b3, (size_t)2 * S}};
+  for (auto &it : items) {
+    CU(it.dst->ensure(std::max<size_t>(it.n, 1) * 4));
+    if (it.src)
+      CU(cudaMemcpyAsync(it.dst->p, it.src, it.n * 4, cudaMemcpyDeviceToDevice, s));
+    else
+      CU(cudaMemsetAsync(it.dst->p, 0, it.n * 4, s));
+  }
+  CU(cudaStreamSynchronize(s));
+  h->set = true;
+  return RCU_OK;
+}
+
+extern "C" int rssm_unroll(rcu_rssm_t h, int T, int B, const float *state0, const float *belief0,
+                           const float *actions, const float *eps, float *means, float *stds,
+                           float *states, float *beliefs, void *stream) {
+  if (!h) return fail(RCU_ERR_INVALID, "rssm_unroll: NULL handle");
+  h->launches = 0;
+  if (!h->set) return fail(RCU_ERR_STATE, "rssm_unroll: weights not set");
+  if (T < 0 || B < 0) return fail(RCU_ERR_INVALID, "rssm_unroll: T and B must be >= 0");
+  if (T == 0 || B == 0) return RCU_OK;
+  if ((h->A > 0 && !actions) || !eps || !means || !stds || !states || !beliefs)
+    return fail(RCU_ERR_INVALID, "rssm_unroll: actions, eps and all outputs are required");
+  RssmParams p{};
+  p.S = h->S; p.A = h->A; p.Hd = h->Hd; p.RH = h->RH; p.T = T; p.B = B;
+  p.W1 = (const float *)h->W1.p; p.b1 = (const float *)h->b1.p;
+  p.Wih = (const float *)h->Wih.p; p.Whh = (const float *)h->Whh.p;
+  p.bih = (const float *)h->bih.p; p.bhh = (const float *)h->bhh.p;
+  p.W2 = (const float *)h->W2.p; p.b2 = (const float *)h->b2.p;
+  p.W3 = (const float *)h->W3.p; p.b3 = (const float *)h->b3.p;
+  p.state0 = state0; p.belief0 = belief0; p.actions = actions; p.eps = eps;
+  p.means = means; p.stds = stds; p.states = states; p.beliefs = beliefs;
+  int clusters = 0;
+  cudaError_t e = launch_rssm(p, h->nsm, (cudaStream_t)stream, &clusters);
+  if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rssm kernel launch: %s", cudaGetErrorString(e));
+  h->launches = 1;
+  return RCU_OK;
+}
+
+extern "C" int rssm_get_status(rcu_rssm_t h, void *stream) {
+  if (!h) return fail(RCU_ERR_INVALID, "rssm_get_status: NULL handle");
+  CU(cudaStreamSynchronize((cudaStream_t)stream));
+  CU(cudaGetLastError());
+  return RCU_OK;
+}
+
+extern "C" int rssm_last_launch_count(rcu_rssm_t h) { return h ? h->launches : -1; }
+
+extern "C" int rssm_destroy(rcu_rssm_t h) {
+  if (!h) return RCU_OK;
+  cudaDeviceSynchronize();
+  delete h;
+  return RCU_OK;
+}

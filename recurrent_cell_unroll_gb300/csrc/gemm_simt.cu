@@ -1,0 +1,121 @@
+// Portable CUDA-core GEMM for the time-parallel input projection
+// G = X W_ih^T + b over all timesteps at once (the "initial input-hidden
+// dense" of "[TOPI] TE implementation of LSTM using scan", apache/tvm PR
+// 11531).  Used for the fp32 path (fp32 FFMA keeps full single precision)
+// and as the portable fallback of the bf16 path.
+//
+// Tile 128x128x16, 256 threads, 8x8 outputs per thread, double-buffered
+// shared memory.  Operands may be fp32 or bf16; accumulation is fp32.
+#include "common.cuh"
+#include "internal.h"
+
+namespace rcu {
+
+namespace {
+
+constexpr int BM = 128, BN = 128, BK = 16, NT = 256;
+
+template <typename T>
+__device__ __forceinline__ float ldf(const T *p) { return Op<T>::load(p); }
+
+template <typename XT, typename WT>
+__global__ void __launch_bounds__(NT) gemm_simt_kernel(const XT *__restrict__ X, int ldx,
+                                                       const WT *__restrict__ W, int ldw,
+                                                       const float *__restrict__ bias,
+                                                       float *__restrict__ G, int ldg, int M,
+                                                       const int32_t *__restrict__ M_dev, int N,
+                                                       int K) {
+  if (M_dev) M = *M_dev;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  if (m0 >= M) return;
+  __shared__ __align__(16) float As[2][BK][BM + 4];
+  __shared__ __align__(16) float Bs[2][BK][BN + 4];
+  const int tid = threadIdx.x;
+  // loader mapping: 128 rows x 16 k, each thread 8 consecutive k of one row
+  const int lr = tid >> 1, lk = (tid & 1) * 8;
+  // compute mapping: 16 x 16 threads, each 8 rows (2 groups of 4) x 8 cols
+  const int ty = tid >> 4, tx = tid & 15;
+
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+
+  float ra[8], rb[8];
+  auto load_regs = [&](int k0) {
+    const int am = m0 + lr, bn = n0 + lr;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int k = k0 + lk + q;
+      ra[q] = (am < M && k < K) ? ldf(X + (size_t)am * ldx + k) : 0.f;
+      rb[q] = (bn < N && k < K) ? ldf(W + (size_t)bn * ldw + k) : 0.f;
+    }
+  };
+  auto store_smem = [&](int buf) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      As[buf][lk + q][lr] = ra[q];
+      Bs[buf][lk + q][lr] = rb[q];
+    }
+  };
+
+  const int nk = ceil_div(K, BK);
+  load_regs(0);
+  store_smem(0);
+  __syncthreads();
+  for (int kt = 0; kt < nk; ++kt) {
+    const int buf = kt & 1;
+    if (kt + 1 < nk) load_regs((kt + 1) * BK);
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      float a[8], b[8];
+      const float4 a0 = *reinterpret_cast<const float4 *>(&As[buf][kk][ty * 4]);
+      const float4 a1 = *reinterpret_cast<const float4 *>(&As[buf][kk][64 + ty * 4]);
+      const float4 b0 = *reinterpret_cast<const float4 *>(&Bs[buf][kk][tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4 *>(&Bs[buf][kk][64 + tx * 4]);
+      a[0] = a0.x; a[1] = a0.y; a[2] = a0.z; a[3] = a0.w;
+      a[4] = a1.x; a[5] = a1.y; a[6] = a1.z; a[7] = a1.w;
+      b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
+      b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    if (kt + 1 < nk) store_smem(buf ^ 1);
+    __syncthreads();
+  }
+
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int m = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
+    if (m >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int n = n0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + (j - 4));
+      if (n < N) G[(size_t)m * ldg + n] = acc[i][j] + (bias ? bias[n] : 0.f);
+    }
+  }
+}
+
+}  // namespace
+
+template <typename XT, typename WT>
+cudaError_t launch_gemm_simt(const XT *X, int ldx, const WT *W, int ldw, const float *bias,
+                             float *G, int ldg, int M, const int32_t *M_dev, int N, int K,
+                             cudaStream_t s) {
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  dim3 grid(ceil_div(N, BN), ceil_div(M, BM));
+  gemm_simt_kernel<XT, WT><<<grid, NT, 0, s>>>(X, ldx, W, ldw, bias, G, ldg, M, M_dev, N, K);
+  return cudaGetLastError();
+}
+
+template cudaError_t launch_gemm_simt<float, float>(const float *, int, const float *, int,
+                                                    const float *, float *, int, int,
+                                                    const int32_t *, int, int, cudaStream_t);
+template cudaError_t launch_gemm_simt<__nv_bfloat16, __nv_bfloat16>(
+    const __nv_bfloat16 *, int, const __nv_bfloat16 *, int, const float *, float *, int, int,
+    const int32_t *, int, int, cudaStream_t);
+
+}  // namespace rcu

@@ -1,0 +1,80 @@
+// Internal launchers shared by the host API (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rcu {
+
+// Packing metadata for one forward (device int32 arrays inside the workspace).
+struct Meta {
+  int32_t *sorted_idx;   // [B] original row at sorted position s
+  int32_t *unsorted_idx; // [B] sorted position of original row b
+  int32_t *lens_sorted;  // [B] length of the row at sorted position s
+  int32_t *batch_sizes;  // [T] rows with length > t
+  int32_t *step_off;     // [T+1] exclusive prefix of batch_sizes; step_off[T] = packed rows
+};
+
+// ---- pack.cu -------------------------------------------------------------
+// Build Meta from lengths (NULL = every row has length T).  Lengths outside
+// [1, T] raise DEV_LENGTHS in *err and are clamped so later kernels stay in bounds.
+cudaError_t launch_meta(const int32_t *lengths, int B, int T, Meta m, int *err, cudaStream_t s);
+// Gather x [T,B,in] (fp32) into packed order (step_off[t] + s) and convert to OT.
+template <typename OT>
+cudaError_t launch_pack_rows(const float *x, int T, int B, int in, Meta m, OT *out, int ld_out,
+                             cudaStream_t s);
+// Zero y[t, b, :] for t >= lengths[b] (varlen only).
+cudaError_t launch_zero_tail(float *y, const int32_t *lengths, int T, int B, int width,
+                             int *err, cudaStream_t s);
+// Convert fp32 [n] to OT (weights / bias preparation).
+template <typename OT>
+cudaError_t launch_convert(const float *src, OT *dst, size_t n, cudaStream_t s);
+
+// ---- gemm_simt.cu ----------------------------------------------------------
+// G[m, n] = sum_k X[m, k] * W[n, k] + bias[n] for m < *M_dev (or M when M_dev
+// is NULL).  Row-major; ldx/ldw/ldg are row strides in elements.
+template <typename XT, typename WT>
+cudaError_t launch_gemm_simt(const XT *X, int ldx, const WT *W, int ldw, const float *bias,
+                             float *G, int ldg, int M, const int32_t *M_dev, int N, int K,
+                             cudaStream_t s);
+
+// ---- recurrent_simt.cu -------------------------------------------------------
+struct RecParams {
+  int T, B, H, Hout, Kp, Hp, nG, D, cell, proj;
+  int U, NU, Rp;   // units per CTA, unit groups per direction, padded gate rows per CTA
+  int Pc, Pcp, NP; // projection rows per CTA (padded), CTAs with projection rows
+  int CB;          // batch rows per chunk (multiple of 4, <= 32)
+  Meta meta;
+  const float *G;
+  int ldG;                // G row stride; direction d's gates start at column d*nG*H
+  const void *Whh[2];     // [NU][Kp][Rp] per direction, WT
+  const void *Whr[2];     // [NP][Hp][Pcp] per direction, WT (projection only)
+  const float *bhn[2];    // GRU hidden-side n-gate bias [H] (NULL = zero)
+  const float *h0, *c0;   // [D][B][Hout], [D][B][H] original row order (NULL = zero)
+  float *h_n, *c_n;       // [D][B][Hout], [D][B][H] or NULL
+  float *y;               // last layer: [T][B][D*Hout] original order, or NULL
+  void *ymid;             // other layers: packed [M][D*Hout] (OT), or NULL
+  void *hx;               // exchange [D][2][B][Kp] (OT)
+  void *mx;               // projection input exchange [D][B][Hp] (OT)
+  float *hst, *cst;       // fp32 state [D][B][Hout], [D][B][H]
+  unsigned *ctr;          // [D] barrier counters (zeroed before launch)
+  int *err;
+  uint64_t timeout_ns;
+  int drop_arrival;
+};
+// wbf16: weights stored bf16 (operands bf16) vs fp32.
+cudaError_t launch_recurrent_simt(const RecParams &p, bool wbf16, int nsm, cudaStream_t s);
+size_t recurrent_simt_smem(const RecParams &p, bool wbf16);
+
+// ---- rssm.cu -----------------------------------------------------------------
+struct RssmParams {
+  int S, A, Hd, RH, T, B;
+  const float *W1, *b1, *Wih, *Whh, *bih, *bhh, *W2, *b2, *W3, *b3; // PyTorch layout, fp32
+  const float *state0, *belief0, *actions, *eps;
+  float *means, *stds, *states, *beliefs;
+};
+cudaError_t launch_rssm(const RssmParams &p, int nsm, cudaStream_t s, int *clusters_used);
+bool rssm_supported(int S, int A, int Hd, int RH);
+
+}  // namespace rcu

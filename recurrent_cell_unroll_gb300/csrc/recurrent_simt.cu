@@ -1,0 +1,329 @@
+// Persistent recurrent kernel, CUDA-core version (fp32 path and portable
+// fallback of the bf16 path).
+//
+// One cooperative launch runs every timestep of one layer (both directions
+// at once).  CTA (d, ug) owns hidden units [ug*U, ug*U+U) of direction d and
+// keeps the matching rows of W_hh (all gates of those units) resident in
+// shared memory for the whole sequence.  Per step it
+//   1. reads h_{t-1} of the active rows (the packed prefix) from the
+//      exchange buffer in L2,
+//   2. computes its slice of h_{t-1} W_hh^T (the "recurrent hidden-hidden
+//      dense" of "[TOPI] TE implementation of LSTM using scan",
+//      apache/tvm PR 11531) with fp32 FFMA,
+//   3. adds the precomputed input projection G, applies the gate
+//      nonlinearities and the cell update in registers, and writes h_t
+//      (exchange buffer, output) — cell state never leaves the CTA,
+//   4. for LSTMP, a second phase computes h_t = W_hr m_t (the
+//      "hidden-projection dense"; projection rows also resident),
+//   5. crosses the step with a bounded group barrier over the CTAs of its
+//      direction.
+// Rows whose length is exhausted drop out of the active prefix (rows are
+// sorted by length), so padding costs nothing ("RNN Op Changes",
+// apache/mxnet issue 9543).  The backward direction runs row s at time
+// len_s - 1 - step.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace rcu {
+
+namespace {
+
+constexpr int NT = 256;
+
+__device__ __forceinline__ void load4(const float *p, float (&w)[4]) {
+  const float4 v = *reinterpret_cast<const float4 *>(p);
+  w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16 *p, float (&w)[4]) {
+  const uint2 v = *reinterpret_cast<const uint2 *>(p);
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&v.x);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&v.y);
+  const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+  w[0] = fa.x; w[1] = fa.y; w[2] = fb.x; w[3] = fb.y;
+}
+// 4 consecutive exchange values from L2 (bypassing L1: written by other CTAs)
+__device__ __forceinline__ void ldcg4(const float *p, float (&w)[4]) {
+  const float4 v = __ldcg(reinterpret_cast<const float4 *>(p));
+  w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+}
+__device__ __forceinline__ void ldcg4(const __nv_bfloat16 *p, float (&w)[4]) {
+  const uint2 v = __ldcg(reinterpret_cast<const uint2 *>(p));
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&v.x);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&v.y);
+  const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+  w[0] = fa.x; w[1] = fa.y; w[2] = fb.x; w[3] = fb.y;
+}
+
+struct Split {
+  int tiles, ks, kc;
+};
+__host__ __device__ inline Split make_split(int CB, int Rx, int Kx) {
+  Split s;
+  s.tiles = (CB / 4) * (Rx / 4);
+  int ks = NT / s.tiles;
+  if (ks < 1) ks = 1;
+  if (ks > Kx / 4) ks = Kx / 4;
+  if (ks < 1) ks = 1;
+  s.ks = ks;
+  s.kc = ceil_div(Kx / 4, ks) * 4;
+  return s;
+}
+
+// red[ks][i][r] = sum over this thread's k range of hs[k][i] * Wsm[k][r]
+template <typename WT>
+__device__ __forceinline__ void chunk_matmul(const WT *Wsm, int Rx, int Kx, const float *hs,
+                                             int CB, float *red, Split sp) {
+  const int tid = threadIdx.x;
+  if (tid >= sp.tiles * sp.ks) return;
+  const int tile = tid % sp.tiles, ks = tid / sp.tiles;
+  const int nrt = Rx / 4;
+  const int ir = tile % nrt, ii = tile / nrt;
+  const int k0 = ks * sp.kc, k1 = min(Kx, k0 + sp.kc);
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  const float *hp = hs + ii * 4;
+  const WT *wp = Wsm + ir * 4;
+#pragma unroll 4
+  for (int k = k0; k < k1; ++k) {
+    const float4 hv = *reinterpret_cast<const float4 *>(hp + (size_t)k * CB);
+    float w[4];
+    load4(wp + (size_t)k * Rx, w);
+    const float h[4] = {hv.x, hv.y, hv.z, hv.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(h[i], w[j], acc[i][j]);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float4 v = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    *reinterpret_cast<float4 *>(red + ((size_t)(ks * CB + ii * 4 + i)) * Rx + ir * 4) = v;
+  }
+}
+
+// hs[k][i] = src[(row0 + i) * ld + k] for i < nr (0 for i >= nr), k < Kx
+template <typename WT>
+__device__ __forceinline__ void load_chunk_T(const WT *src, int ld, int row0, int nr, int Kx,
+                                             int CB, float *hs) {
+  const int nq = Kx / 4;
+  for (int e = threadIdx.x; e < CB * nq; e += NT) {
+    const int i = e % CB, k = (e / CB) * 4;
+    float v[4] = {0.f, 0.f, 0.f, 0.f};
+    if (i < nr) ldcg4(src + (size_t)(row0 + i) * ld + k, v);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) hs[(size_t)(k + q) * CB + i] = v[q];
+  }
+}
+
+__device__ __forceinline__ float red_sum(const float *red, int ks, int CB, int Rx, int i, int r) {
+  float a = 0.f;
+  for (int q = 0; q < ks; ++q) a += red[((size_t)(q * CB + i)) * Rx + r];
+  return a;
+}
+
+template <typename WT>
+__global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int d = blockIdx.x / p.NU;
+  const int ug = blockIdx.x % p.NU;
+  const int u0 = ug * p.U;
+  const int B = p.B, H = p.H, Hout = p.Hout, Kp = p.Kp, Hp = p.Hp, U = p.U, CB = p.CB;
+  const int nG = p.nG;
+  const bool lstm = p.cell == CELL_LSTM;
+  const bool proj = p.proj > 0;
+  const bool prow = proj && ug < p.NP;  // owns projection rows
+  const int pr0 = ug * p.Pc;
+
+  WT *Ws = reinterpret_cast<WT *>(smem);
+  WT *Wr = Ws + (size_t)Kp * p.Rp;
+  float *hs = reinterpret_cast<float *>(
+      smem + round_up_sz(((size_t)Kp * p.Rp + (proj ? (size_t)Hp * p.Pcp : 0)) * sizeof(WT), 16));
+  const int Kh = max(Kp, proj ? Hp : 0);
+  float *red = hs + (size_t)Kh * CB;
+
+  {  // resident weights
+    const WT *gW = reinterpret_cast<const WT *>(p.Whh[d]) + (size_t)ug * Kp * p.Rp;
+    for (int i = threadIdx.x; i < Kp * p.Rp; i += NT) Ws[i] = gW[i];
+    if (prow) {
+      const WT *gR = reinterpret_cast<const WT *>(p.Whr[d]) + (size_t)ug * Hp * p.Pcp;
+      for (int i = threadIdx.x; i < Hp * p.Pcp; i += NT) Wr[i] = gR[i];
+    }
+  }
+  const float *bhn = p.bhn[d];
+  WT *hx = reinterpret_cast<WT *>(p.hx) + (size_t)d * 2 * B * Kp;
+  WT *mx = reinterpret_cast<WT *>(p.mx) + (size_t)d * B * Hp;
+  float *hst = p.hst + (size_t)d * B * Hout;
+  float *cst = p.cst + (size_t)d * B * H;
+  const int32_t *sidx = p.meta.sorted_idx;
+  const int32_t *lens = p.meta.lens_sorted;
+  const int32_t *bsz = p.meta.batch_sizes;
+  const int32_t *soff = p.meta.step_off;
+  const int ldo = p.D * Hout;
+
+  // initial state of the entries this CTA owns
+  for (int e = threadIdx.x; e < B * U; e += NT) {
+    const int s = e / U, u = u0 + e % U;
+    if (u >= H) continue;
+    const int b = sidx[s];
+    if (lstm) cst[(size_t)s * H + u] = p.c0 ? p.c0[((size_t)d * B + b) * H + u] : 0.f;
+    if (!proj) {
+      const float h = p.h0 ? p.h0[((size_t)d * B + b) * Hout + u] : 0.f;
+      hst[(size_t)s * Hout + u] = h;
+      hx[(size_t)s * Kp + u] = Op<WT>::from_f(h);
+    }
+  }
+  if (prow) {
+    for (int e = threadIdx.x; e < B * p.Pc; e += NT) {
+      const int s = e / p.Pc, q = pr0 + e % p.Pc;
+      if (q >= Hout) continue;
+      const float h = p.h0 ? p.h0[((size_t)d * B + sidx[s]) * Hout + q] : 0.f;
+      hst[(size_t)s * Hout + q] = h;
+      hx[(size_t)s * Kp + q] = Op<WT>::from_f(h);
+    }
+  }
+  unsigned nbar = 0;
+  unsigned *ctr = p.ctr + d;
+  const bool drop = p.drop_arrival && blockIdx.x == 0;
+  if (!group_barrier(ctr, ++nbar * p.NU, p.err, p.timeout_ns, drop)) return;
+
+  const Split sp1 = make_split(CB, p.Rp, Kp);
+  const Split sp2 = proj ? make_split(CB, p.Pcp, Hp) : Split{0, 0, 0};
+
+  for (int step = 0; step < p.T; ++step) {
+    const int nact = bsz[step];
+    if (nact <= 0) break;
+    const WT *hcur = hx + (size_t)(step & 1) * B * Kp;
+    WT *hnxt = hx + (size_t)((step & 1) ^ 1) * B * Kp;
+
+    // ---- phase 1: gates and cell update for this CTA's units
+    for (int cb = 0; cb < nact; cb += CB) {
+      const int nr = min(CB, nact - cb);
+      __syncthreads();
+      load_chunk_T(hcur, Kp, cb, nr, Kp, CB, hs);
+      __syncthreads();
+      chunk_matmul(Ws, p.Rp, Kp, hs, CB, red, sp1);
+      __syncthreads();
+      for (int e = threadIdx.x; e < nr * U; e += NT) {
+        const int i = e / U, j = e % U, u = u0 + j;
+        if (u >= H) continue;
+        const int s = cb + i;
+        const int tt = d == 0 ? step : lens[s] - 1 - step;
+        const size_t row = (size_t)soff[tt] + s;
+        const float *g = p.G + row * p.ldG + (size_t)d * nG * H + u;
+        float hv;
+        if (lstm) {
+          const float ai = red_sum(red, sp1.ks, CB, p.Rp, i, 0 * U + j) + __ldg(g + 0 * H);
+          const float af = red_sum(red, sp1.ks, CB, p.Rp, i, 1 * U + j) + __ldg(g + 1 * H);
+          const float ag = red_sum(red, sp1.ks, CB, p.Rp, i, 2 * U + j) + __ldg(g + 2 * H);
+          const float ao = red_sum(red, sp1.ks, CB, p.Rp, i, 3 * U + j) + __ldg(g + 3 * H);
+          const float ig = sigmoid_f(ai), fg = sigmoid_f(af), gg = tanh_f(ag), og = sigmoid_f(ao);
+          float c = cst[(size_t)s * H + u];
+          c = fg * c + ig * gg;
+          cst[(size_t)s * H + u] = c;
+          hv = og * tanh_f(c);
+          if (proj) {
+            mx[(size_t)s * Hp + u] = Op<WT>::from_f(hv);
+            continue;
+          }
+        } else {
+          const float hr = red_sum(red, sp1.ks, CB, p.Rp, i, 0 * U + j);
+          const float hz = red_sum(red, sp1.ks, CB, p.Rp, i, 1 * U + j);
+          const float hn = red_sum(red, sp1.ks, CB, p.Rp, i, 2 * U + j) + (bhn ? bhn[u] : 0.f);
+          const float rg = sigmoid_f(__ldg(g + 0 * H) + hr);
+          const float zg = sigmoid_f(__ldg(g + 1 * H) + hz);
+          const float ng = tanh_f(__ldg(g + 2 * H) + rg * hn);
+          const float hprev = hst[(size_t)s * Hout + u];
+          hv = (1.f - zg) * ng + zg * hprev;
+        }
+        hst[(size_t)s * Hout + u] = hv;
+        hnxt[(size_t)s * Kp + u] = Op<WT>::from_f(hv);
+        if (p.y) p.y[((size_t)tt * B + sidx[s]) * ldo + (size_t)d * Hout + u] = hv;
+        if (p.ymid)
+          reinterpret_cast<WT *>(p.ymid)[row * ldo + (size_t)d * Hout + u] = Op<WT>::from_f(hv);
+      }
+    }
+    if (!group_barrier(ctr, ++nbar * p.NU, p.err, p.timeout_ns)) return;
+
+    // ---- phase 2 (LSTMP): h_t = W_hr m_t for this CTA's projection rows
+    if (proj) {
+      if (prow) {
+        for (int cb = 0; cb < nact; cb += CB) {
+          const int nr = min(CB, nact - cb);
+          __syncthreads();
+          load_chunk_T(mx, Hp, cb, nr, Hp, CB, hs);
+          __syncthreads();
+          chunk_matmul(Wr, p.Pcp, Hp, hs, CB, red, sp2);
+          __syncthreads();
+          for (int e = threadIdx.x; e < nr * p.Pc; e += NT) {
+            const int i = e / p.Pc, j = e % p.Pc, q = pr0 + j;
+            if (q >= Hout) continue;
+            const int s = cb + i;
+            const int tt = d == 0 ? step : lens[s] - 1 - step;
+            const size_t row = (size_t)soff[tt] + s;
+            const float hv = red_sum(red, sp2.ks, CB, p.Pcp, i, j);
+            hst[(size_t)s * Hout + q] = hv;
+            hnxt[(size_t)s * Kp + q] = Op<WT>::from_f(hv);
+            if (p.y) p.y[((size_t)tt * B + sidx[s]) * ldo + (size_t)d * Hout + q] = hv;
+            if (p.ymid)
+              reinterpret_cast<WT *>(p.ymid)[row * ldo + (size_t)d * Hout + q] =
+                  Op<WT>::from_f(hv);
+          }
+        }
+      }
+      if (!group_barrier(ctr, ++nbar * p.NU, p.err, p.timeout_ns)) return;
+    }
+  }
+
+  // final state of each row = state after its last processed step
+  for (int e = threadIdx.x; e < B * U; e += NT) {
+    const int s = e / U, u = u0 + e % U;
+    if (u >= H) continue;
+    const int b = sidx[s];
+    if (lstm && p.c_n) p.c_n[((size_t)d * B + b) * H + u] = cst[(size_t)s * H + u];
+    if (!proj && p.h_n) p.h_n[((size_t)d * B + b) * Hout + u] = hst[(size_t)s * Hout + u];
+  }
+  if (prow && p.h_n) {
+    for (int e = threadIdx.x; e < B * p.Pc; e += NT) {
+      const int s = e / p.Pc, q = pr0 + e % p.Pc;
+      if (q >= Hout) continue;
+      p.h_n[((size_t)d * B + sidx[s]) * Hout + q] = hst[(size_t)s * Hout + q];
+    }
+  }
+}
+
+}  // namespace
+
+size_t recurrent_simt_smem(const RecParams &p, bool wbf16) {
+  const size_t ws = wbf16 ? 2 : 4;
+  const bool proj = p.proj > 0;
+  size_t bytes = round_up_sz(((size_t)p.Kp * p.Rp + (proj ? (size_t)p.Hp * p.Pcp : 0)) * ws, 16);
+  const int Kh = std::max(p.Kp, proj ? p.Hp : 0);
+  bytes += (size_t)Kh * p.CB * 4;
+  const Split s1 = make_split(p.CB, p.Rp, p.Kp);
+  size_t red = (size_t)s1.ks * p.CB * p.Rp;
+  if (proj) {
+    const Split s2 = make_split(p.CB, p.Pcp, p.Hp);
+    red = std::max(red, (size_t)s2.ks * p.CB * p.Pcp);
+  }
+  bytes += red * 4;
+  return bytes;
+}
+
+cudaError_t launch_recurrent_simt(const RecParams &p, bool wbf16, int nsm, cudaStream_t s) {
+  (void)nsm;
+  const size_t smem = recurrent_simt_smem(p, wbf16);
+  const void *fn = wbf16 ? (const void *)rec_simt_kernel<__nv_bfloat16>
+                         : (const void *)rec_simt_kernel<float>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  RecParams pc = p;
+  void *args[] = {&pc};
+  return cudaLaunchCooperativeKernel(fn, dim3(p.D * p.NU), dim3(NT), args, smem, s);
+}
+
+}  // namespace rcu

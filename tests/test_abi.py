@@ -1,0 +1,67 @@
+"""CPU-side checks of the C ABI: the library builds, loads, and exports every
+entry point include/rcu.h declares; the Python binding's host logic
+(canonical strides) behaves.  No compute call runs here (no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from recurrent_cell_unroll_gb300 import _build, binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = _build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "rcu.h")).read()
+    return sorted(set(re.findall(r"^RCU_API\s+[\w\s\*]*?\b(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for required in ("rnn_create", "rnn_set_weights", "rnn_forward", "rssm_unroll"):
+        assert required in names
+    assert set(names) == set(binding.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), f"librcu.so does not export {name}"
+
+
+def test_library_exports_nothing_else(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB], capture_output=True,
+                         text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    ours = {n for n in exported if n.startswith(("rnn_", "rssm_", "rcu_"))}
+    assert ours == set(declared_symbols())
+
+
+def test_version_string_without_gpu(lib):
+    lib.rcu_version.restype = ctypes.c_char_p
+    assert b"sm_103a" in lib.rcu_version()
+
+
+def test_canonical_contiguous():
+    base = torch.arange(20, dtype=torch.float32)
+    t = base.as_strided((1, 4, 5), (5, 5, 1))
+    assert t.is_contiguous()
+    c = binding.canonical_contiguous(t)
+    assert c.stride() == (20, 5, 1) and torch.equal(c, t)
+    u = torch.zeros(2, 3, 4)
+    assert binding.canonical_contiguous(u) is u
+    v = torch.zeros(4, 3).t()
+    assert binding.canonical_contiguous(v).stride() == (4, 1)
+
+
+def test_binding_rejects_host_tensors():
+    with pytest.raises(ValueError):
+        binding._dev(torch.zeros(3))

@@ -1,0 +1,287 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerances: fp32 path max-abs error <= 1e-4 on every output after all T
+steps; bf16-weight path max|gpu - ref| / max|ref| <= 2e-2 per output tensor
+(weights rounded to bf16 on both sides); packing indices bit-exact.
+Small cases cover several tiles and ragged tails element by element; the
+full-size workloads are checked on sampled batch rows, which the oracle
+computes exactly (rows are independent).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from recurrent_cell_unroll_gb300 import binding, workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+F32_TOL = 1e-4
+BF16_REL = 2e-2
+
+
+def _rel(a, b):
+    return float(np.abs(a - b).max() / max(np.abs(b).max(), 1e-30))
+
+
+def _cell(spec):
+    return oracle.LSTM if spec.cell == "lstm" else oracle.GRU
+
+
+def run_gpu(spec, inp, force_path=0, bias=True):
+    dev = torch.device("cuda")
+    net = binding.RNN.from_spec(spec)
+    if force_path:
+        net.set_attr(binding.RCU_ATTR_FORCE_PATH, force_path)
+    net.set_weights(inp["weights"])
+    lengths = inp["lengths"].to(dev) if inp["lengths"] is not None else None
+    h0 = inp["h0"].to(dev) if inp["h0"] is not None else None
+    c0 = inp["c0"].to(dev) if inp["c0"] is not None else None
+    y, hn, cn = net.forward(inp["x"].to(dev), lengths=lengths, h0=h0, c0=c0)
+    st = net.status()
+    assert st == 0, f"device status {st}"
+    out = (y.cpu().numpy(), hn.cpu().numpy(), None if cn is None else cn.cpu().numpy())
+    net.close()
+    return out
+
+
+def run_oracle(spec, inp, rows=None):
+    return oracle.rnn_forward(_cell(spec), inp["x"], inp["weights"], hidden=spec.hidden,
+                              proj=spec.proj, bidirectional=spec.bidir, lengths=inp["lengths"],
+                              h0=inp["h0"], c0=inp["c0"], bf16_weights=spec.dtype == "bf16",
+                              rows=rows)
+
+
+def compare(spec, got, ref, rows=None):
+    sel = slice(None) if rows is None else list(rows)
+    pairs = [("y", got[0][:, sel], ref[0][:, sel]), ("h_n", got[1][:, sel], ref[1][:, sel])]
+    if spec.cell == "lstm":
+        pairs.append(("c_n", got[2][:, sel], ref[2][:, sel]))
+    for name, g, r in pairs:
+        assert np.all(np.isfinite(g)), f"{name} not finite"
+        if spec.dtype == "f32":
+            e = float(np.abs(g - r).max())
+            assert e <= F32_TOL, f"{name}: max-abs error {e:.3e} > {F32_TOL}"
+        else:
+            e = _rel(g, r)
+            assert e <= BF16_REL, f"{name}: relative error {e:.3e} > {BF16_REL}"
+
+
+SMALL = [
+    # fp32 LSTM at the TVM benchmark shape (whole config)
+    wl.LSTM_T80,
+    wl.LSTM_T80.scaled(T=9, B=7, in_dim=33, hidden=70, c0_std=0.5, h0_std=0.5),
+    wl.LSTM_T80.scaled(name="lstm2l", layers=2, T=11, B=37, in_dim=20, hidden=45),
+    wl.LSTMP_2L.scaled(T=13, B=5, in_dim=80, hidden=136, proj=40),
+    wl.LSTMP_2L.scaled(dtype="f32", T=7, B=9, in_dim=17, hidden=52, proj=12, h0_std=0.3,
+                       c0_std=0.3),
+    wl.BILSTM_VAR.scaled(T=37, B=13, in_dim=24, hidden=40, varlen=(1, 37)),
+    wl.BILSTM_VAR.scaled(layers=2, T=16, B=6, in_dim=8, hidden=20, varlen=(3, 16)),
+    wl.GRU_3L.scaled(T=20, B=37, in_dim=72, hidden=200),
+    wl.GRU_3L.scaled(dtype="f32", layers=2, bidir=True, T=9, B=5, in_dim=16, hidden=24,
+                     varlen=(1, 9)),
+    wl.GRU_3L.scaled(layers=1, T=5, B=1, in_dim=8, hidden=1024),
+]
+
+
+@pytest.mark.parametrize("spec", SMALL, ids=lambda s: f"{s.name}-T{s.T}-B{s.B}-H{s.hidden}")
+@pytest.mark.parametrize("path", [0, 1], ids=["auto", "simt"])
+def test_small_parity(spec, path):
+    inp = wl.make_rnn_inputs(spec, seed=11)
+    compare(spec, run_gpu(spec, inp, force_path=path), run_oracle(spec, inp))
+
+
+def test_no_bias_equals_zero_bias():
+    spec = wl.LSTM_T80.scaled(T=6, B=4, in_dim=10, hidden=12)
+    inp = wl.make_rnn_inputs(spec, seed=3, bias=False)
+    got = run_gpu(spec, inp)
+    for w in inp["weights"]:
+        w["b_ih"] = torch.zeros(4 * 12)
+        w["b_hh"] = torch.zeros(4 * 12)
+    ref = run_gpu(spec, inp)
+    for a, b in zip(got, ref):
+        np.testing.assert_array_equal(a, b)
+    compare(spec, got, run_oracle(spec, inp))
+
+
+def test_pack_indices_bit_exact():
+    spec = wl.BILSTM_VAR
+    inp = wl.make_rnn_inputs(spec.scaled(in_dim=8, hidden=8), seed=0)
+    dev = torch.device("cuda")
+    net = binding.RNN("lstm", 1, 8, 8, bidirectional=True)
+    net.set_weights(inp["weights"])
+    lengths = inp["lengths"].to(dev)
+    net.forward(inp["x"].to(dev), lengths=lengths)
+    s = torch.empty(spec.B, dtype=torch.int32, device=dev)
+    u = torch.empty_like(s)
+    bs = torch.empty(spec.T, dtype=torch.int32, device=dev)
+    binding.rnn_get_pack(net.h, s, u, bs)
+    assert net.status() == 0
+    rs, ru, rbs = oracle.pack(inp["lengths"], spec.T)
+    assert np.array_equal(s.cpu().numpy(), rs)
+    assert np.array_equal(u.cpu().numpy(), ru)
+    assert np.array_equal(bs.cpu().numpy(), rbs)
+    net.close()
+
+
+def test_padding_is_zero_and_state_at_true_end():
+    spec = wl.BILSTM_VAR.scaled(T=20, B=6, in_dim=5, hidden=7, varlen=(1, 20))
+    inp = wl.make_rnn_inputs(spec, seed=4)
+    got = run_gpu(spec, inp)
+    L = inp["lengths"].numpy()
+    for b in range(spec.B):
+        assert np.all(got[0][L[b]:, b] == 0.0)
+    compare(spec, got, run_oracle(spec, inp))
+
+
+def test_rows_sorted_equal_lengths_and_single_step():
+    spec = wl.BILSTM_VAR.scaled(T=1, B=3, in_dim=4, hidden=5, varlen=(1, 1))
+    inp = wl.make_rnn_inputs(spec, seed=5)
+    compare(spec, run_gpu(spec, inp), run_oracle(spec, inp))
+    spec = wl.GRU_3L.scaled(dtype="f32", layers=1, bidir=True, T=6, B=4, in_dim=4, hidden=5,
+                            varlen=(6, 6))
+    inp = wl.make_rnn_inputs(spec, seed=6)
+    compare(spec, run_gpu(spec, inp), run_oracle(spec, inp))
+
+
+def test_non_canonical_strides_give_same_result():
+    spec = wl.LSTM_T80.scaled(T=1, B=4, in_dim=5, hidden=6)
+    inp = wl.make_rnn_inputs(spec, seed=7)
+    dev = torch.device("cuda")
+    net = binding.RNN.from_spec(spec)
+    net.set_weights(inp["weights"])
+    x = inp["x"].to(dev)
+    y1, _, _ = net.forward(x)
+    x_odd = x.reshape(-1).as_strided((1, 4, 5), (5, 5, 1))  # passes is_contiguous()
+    y2, _, _ = net.forward(x_odd)
+    assert net.status() == 0
+    assert torch.equal(y1, y2)
+    net.close()
+
+
+def test_deterministic_repeat():
+    spec = wl.GRU_3L.scaled(T=10, B=9, in_dim=32, hidden=64)
+    inp = wl.make_rnn_inputs(spec, seed=8)
+    a = run_gpu(spec, inp)
+    b = run_gpu(spec, inp)
+    for x, y in zip(a, b):
+        if x is not None:
+            np.testing.assert_array_equal(x, y)
+
+
+def test_errors_are_reported():
+    with pytest.raises(binding.RcuError) as e:
+        binding.rnn_create(binding.RCU_GRU, 1, 4, 8, 2, binding.RCU_F32)
+    assert e.value.code == binding.RCU_ERR_UNSUPPORTED
+    with pytest.raises(binding.RcuError):
+        binding.rnn_create(binding.RCU_LSTM, 0, 4, 8, 0, binding.RCU_F32)
+    net = binding.RNN("lstm", 1, 4, 8)
+    with pytest.raises(binding.RcuError) as e:
+        net.forward(torch.zeros(3, 2, 4, device="cuda"))
+    assert e.value.code == binding.RCU_ERR_STATE
+    net.close()
+
+
+def test_bad_lengths_flagged_on_device():
+    spec = wl.BILSTM_VAR.scaled(T=5, B=3, in_dim=4, hidden=4, varlen=(1, 5))
+    inp = wl.make_rnn_inputs(spec, seed=9)
+    dev = torch.device("cuda")
+    net = binding.RNN.from_spec(spec)
+    net.set_weights(inp["weights"])
+    lengths = torch.tensor([5, 0, 7], dtype=torch.int32, device=dev)
+    net.forward(inp["x"].to(dev), lengths=lengths)
+    assert net.status() == binding.RCU_ERR_LENGTHS
+    y, _, _ = net.forward(inp["x"].to(dev), lengths=inp["lengths"].to(dev))
+    assert net.status() == 0
+    net.close()
+
+
+def test_barrier_wait_times_out_and_context_survives():
+    """One CTA never arrives at the first step barrier: every wait must end
+    with RCU_ERR_TIMEOUT within the bound, and the next call must work."""
+    spec = wl.LSTM_T80.scaled(T=4, B=2, in_dim=8, hidden=64)
+    inp = wl.make_rnn_inputs(spec, seed=10)
+    dev = torch.device("cuda")
+    net = binding.RNN.from_spec(spec)
+    net.set_weights(inp["weights"])
+    net.set_attr(binding.RCU_ATTR_BARRIER_TIMEOUT_NS, 50_000_000)
+    net.set_attr(binding.RCU_ATTR_FORCE_PATH, 1)
+    net.set_attr(binding.RCU_ATTR_TEST_DROP_ARRIVAL, 1)
+    net.forward(inp["x"].to(dev))
+    assert net.status() == binding.RCU_ERR_TIMEOUT
+    net.set_attr(binding.RCU_ATTR_TEST_DROP_ARRIVAL, 0)
+    y, hn, cn = net.forward(inp["x"].to(dev))
+    assert net.status() == 0
+    ref = run_oracle(spec, inp)
+    assert np.abs(y.cpu().numpy() - ref[0]).max() <= F32_TOL
+    net.close()
+
+
+def test_two_handles_two_threads():
+    import threading
+    spec_a = wl.LSTM_T80.scaled(T=7, B=3, in_dim=9, hidden=33)
+    spec_b = wl.GRU_3L.scaled(dtype="f32", layers=1, T=5, B=4, in_dim=6, hidden=17)
+    ia, ib = wl.make_rnn_inputs(spec_a, seed=12), wl.make_rnn_inputs(spec_b, seed=13)
+    results = {}
+
+    def work(name, spec, inp):
+        with torch.cuda.stream(torch.cuda.Stream()):
+            results[name] = run_gpu(spec, inp)
+
+    ts = [threading.Thread(target=work, args=("a", spec_a, ia)),
+          threading.Thread(target=work, args=("b", spec_b, ib))]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    compare(spec_a, results["a"], run_oracle(spec_a, ia))
+    compare(spec_b, results["b"], run_oracle(spec_b, ib))
+
+
+# ----------------------------------------------------------------------------- RSSM
+
+@pytest.mark.parametrize("spec", [
+    wl.RSSM_B50,
+    wl.RSSM_B50.scaled(T=7, B=3, state_dim=5, action_dim=0, hidden=33, rnn_hidden=17,
+                       state0_std=1.0, belief0_std=0.5),
+    wl.RSSM_B50.scaled(T=4, B=70, state_dim=30, action_dim=3, hidden=64, rnn_hidden=96),
+], ids=lambda s: f"T{s.T}-B{s.B}-S{s.state_dim}-H{s.hidden}-RH{s.rnn_hidden}")
+def test_rssm_parity(spec):
+    inp = wl.make_rssm_inputs(spec, seed=21)
+    dev = torch.device("cuda")
+    m = binding.RSSM(spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden)
+    m.set_weights(inp["weights"])
+    s0 = inp["state0"].to(dev) if inp["state0"] is not None else None
+    b0 = inp["belief0"].to(dev) if inp["belief0"] is not None else None
+    outs = m.unroll(inp["actions"].to(dev), inp["eps"].to(dev), s0, b0)
+    assert binding.rssm_get_status(m.h) == 0
+    ref = oracle.rssm_unroll(inp["weights"], inp["actions"], inp["eps"], state0=inp["state0"],
+                             belief0=inp["belief0"])
+    for name, o, r in zip(("means", "stds", "states", "beliefs"), outs, ref):
+        e = float(np.abs(o.cpu().numpy() - r).max())
+        assert e <= F32_TOL, f"{name}: max-abs error {e:.3e}"
+    m.close()
+
+
+# ----------------------------------------------------------------------------- full-size workloads
+
+FULL = [
+    (wl.LSTMP_2L, [0, 13, 31]),
+    (wl.BILSTM_VAR, None),       # rows chosen below: longest, shortest, a tie
+    (wl.GRU_3L, [0, 255]),
+]
+
+
+@pytest.mark.parametrize("spec,rows", FULL, ids=lambda v: getattr(v, "name", "rows"))
+def test_full_size_sampled_rows(spec, rows):
+    inp = wl.make_rnn_inputs(spec, seed=0)
+    if rows is None:
+        L = inp["lengths"].numpy()
+        rows = [int(np.argmax(L)), int(np.argmin(L)), 17]
+    got = run_gpu(spec, inp)
+    ref = run_oracle(spec, inp, rows=rows)
+    compare(spec, got, ref, rows=rows)
+    if spec.varlen is not None:
+        L = inp["lengths"].numpy()
+        for b in range(spec.B):
+            assert np.all(got[0][L[b]:, b] == 0.0)
