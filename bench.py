@@ -1,0 +1,575 @@
+"""Benchmark of the time-unrolled recurrent forward pass on GB300.
+
+One "step" = one full forward of the workload through the C ABI (length sort
+and packing, every layer's input-projection GEMM and persistent recurrent
+kernel, output streaming).  Default workload: the 3-layer bf16 GRU
+(T=512, B=256, 1024 -> 1024), the largest of the five shapes; --workload picks
+another.  Metric: (batch x timesteps)/s, i.e. B*T per second of device time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the workload on its
+own GPU (batch rows are independent: weak scaling, no collective on the data
+path); the reported time is the max over ranks.  --impl reference times the
+fp64 CPU oracle on the host cores instead (the only baseline this method has).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from recurrent_cell_unroll_gb300 import workloads as wl  # noqa: E402
+
+WORKLOADS = {
+    "lstm": wl.LSTM_T80, "rssm": wl.RSSM_B50, "lstmp": wl.LSTMP_2L,
+    "bilstm": wl.BILSTM_VAR, "gru": wl.GRU_3L,
+}
+METRIC = "(batch×timesteps)/s"
+UNIT = "(B·T)/s"
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ----------------------------------------------------------------------------- distributed helpers
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, local, ws
+
+
+def dist_init(backend: str):
+    rank, local, ws = dist_info()
+    if ws > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+    return rank, local, ws
+
+
+def dist_barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def dist_max(value: float, device=None) -> float:
+    """Max of a float over all ranks (identity when not distributed)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_sum(value: float, device=None) -> float:
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- workload arithmetic
+
+def units(spec, inp) -> int:
+    """B*T of one step (the metric's unit count; padded T for varlen)."""
+    return spec.B * spec.T
+
+
+def active_rows(spec, inp) -> int:
+    """Sum over rows of processed steps (= B*T without lengths)."""
+    if isinstance(spec, wl.RssmSpec) or inp.get("lengths") is None:
+        return spec.B * spec.T
+    return int(inp["lengths"].sum())
+
+
+def kernel_flops(spec, inp) -> dict:
+    """Algorithmic FLOPs per launch of each kernel kind (2 per multiply-add)."""
+    if isinstance(spec, wl.RssmSpec):
+        S, A, Hd, RH = spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden
+        per = 2 * (Hd * (S + A) + 3 * RH * Hd + 3 * RH * RH + Hd * RH + 2 * S * Hd)
+        return {"rssm": [per * spec.B * spec.T]}
+    M = active_rows(spec, inp)
+    D, nG, H, Ho, P = spec.D, spec.nG, spec.hidden, spec.Hout, spec.proj
+    gemm, rec = [], []
+    for layer in range(spec.layers):
+        K = spec.in_dim if layer == 0 else D * Ho
+        gemm.append(2 * M * D * nG * H * K)
+        rec.append(2 * M * D * (nG * H * Ho + (P * H if P else 0)))
+    return {"input_gemm": gemm, "recurrent": rec}
+
+
+def total_flops(spec, inp) -> int:
+    return sum(sum(v) for v in kernel_flops(spec, inp).values())
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "sm_max_mhz": d.get("sm_max_mhz", 2070.0), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0, "source": "fallback"}
+
+
+def fp32_alu_peak_tflops(nsm: int, mhz: float) -> float:
+    """FFMA peak: SMs x 128 fp32 lanes x 2 FLOP x clock."""
+    return nsm * 128 * 2 * mhz * 1e6 / 1e12
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms in the background."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def make_runner(spec, inp, dev):
+    from recurrent_cell_unroll_gb300 import binding
+    if isinstance(spec, wl.RssmSpec):
+        m = binding.RSSM(spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden)
+        m.set_weights(inp["weights"], device=dev)
+        d = {k: (None if inp[k] is None else inp[k].to(dev)) for k in
+             ("actions", "eps", "state0", "belief0")}
+        T, B, S, RH = spec.T, spec.B, spec.state_dim, spec.rnn_hidden
+        outs = [torch.empty((T, B, S), device=dev) for _ in range(3)] + \
+            [torch.empty((T, B, RH), device=dev)]
+
+        def step():
+            binding.rssm_unroll(m.h, T, B, d["state0"], d["belief0"], d["actions"], d["eps"],
+                                *outs)
+
+        def launches():
+            return binding.rssm_last_launch_count(m.h)
+
+        def profile_on():
+            pass
+
+        def profile_read():
+            return None
+
+        def e2e_io():
+            ins = {k: v for k, v in d.items() if v is not None}
+            return ins, outs
+
+        def status():
+            return binding.rssm_get_status(m.h)
+        return step, launches, profile_on, profile_read, e2e_io, status, m
+
+    net = binding.RNN.from_spec(spec)
+    net.set_weights(inp["weights"], device=dev)
+    d = {k: (None if inp[k] is None else inp[k].to(dev)) for k in ("x", "lengths", "h0", "c0")}
+    T, B = spec.T, spec.B
+    y = torch.empty((T, B, spec.D * spec.Hout), device=dev)
+    hn = torch.empty((spec.layers * spec.D, B, spec.Hout), device=dev)
+    cn = torch.empty((spec.layers * spec.D, B, spec.hidden), device=dev) \
+        if spec.cell == "lstm" else None
+
+    def step():
+        binding.rnn_forward(net.h, T, B, d["x"], d["lengths"], d["h0"], d["c0"], None, y, hn, cn)
+
+    def launches():
+        return net.launch_count()
+
+    def profile_on():
+        net.set_attr(binding.RCU_ATTR_PROFILE, 1)
+        binding.rnn_profile_reset(net.h)
+
+    def profile_read():
+        prof = net.profile()
+        net.set_attr(binding.RCU_ATTR_PROFILE, 0)
+        return prof
+
+    def e2e_io():
+        ins = {k: v for k, v in d.items() if v is not None}
+        outs = [y, hn] + ([cn] if cn is not None else [])
+        return ins, outs
+
+    def status():
+        return net.status()
+    return step, launches, profile_on, profile_read, e2e_io, status, net
+
+
+def roofline(spec, inp, prof, peaks, nsm, step_ms=None):
+    """Roofline of the dominant kernel from the live event timings."""
+    if isinstance(spec, wl.RssmSpec):
+        # one kernel per step: its launch time is the event-timed step
+        per_launch = kernel_flops(spec, inp)["rssm"][0]
+        achieved = per_launch / (step_ms / 1e3) / 1e12
+        peak = fp32_alu_peak_tflops(nsm, peaks["sm_max_mhz"])
+        return {"kernel": "rssm_unroll", "bound": "alu", "achieved": round(achieved, 4),
+                "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(achieved / peak, 6),
+                "traffic": None, "peak_note": "fp32 FFMA: SMs x 128 lanes x 2 x max SM clock",
+                "avg_launch_ms": round(step_ms, 4), "launches": 1,
+                "algorithmic_flop_per_launch": per_launch}
+    if not prof:
+        return None
+    name, (ms, n) = max(prof.items(), key=lambda kv: kv[1][0])
+    fl = kernel_flops(spec, inp)
+    kind = "recurrent" if name.startswith("recurrent") else (
+        "input_gemm" if name.startswith("input_gemm") else None)
+    if kind is None:
+        return None
+    per_launch = sum(fl[kind]) / len(fl[kind])
+    avg_s = ms / 1e3 / n
+    achieved = per_launch / avg_s / 1e12
+    if spec.dtype == "bf16":
+        peak, bound, note = peaks["bf16_tflops_sustained"], "tensor", \
+            f"bf16 dense, sustained, {peaks['source']}"
+    else:
+        peak, bound, note = fp32_alu_peak_tflops(nsm, peaks["sm_max_mhz"]), "alu", \
+            "fp32 FFMA: SMs x 128 lanes x 2 x max SM clock"
+    return {"kernel": name, "bound": bound, "achieved": round(achieved, 3), "peak": round(peak, 1),
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 5), "traffic": None,
+            "peak_note": note, "avg_launch_ms": round(avg_s * 1e3, 4), "launches": n,
+            "algorithmic_flop_per_launch": per_launch}
+
+
+def flush_l2(buf):
+    buf.add_(1.0)
+
+
+def run_ours(args, spec, rank, local, ws):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from recurrent_cell_unroll_gb300 import binding
+    binding.load()
+    inp = (wl.make_rssm_inputs(spec, seed=args.seed + rank) if isinstance(spec, wl.RssmSpec)
+           else wl.make_rnn_inputs(spec, seed=args.seed + rank))
+    step, launches, profile_on, profile_read, e2e_io, status, keep = make_runner(spec, inp, dev)
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    flush = torch.empty(int(2 * L2_BYTES // 4), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        step()
+    st = status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region: K steps, L2 flushed between steps (outside the events)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    profile_on()
+    dist_barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t_wall = time.perf_counter()
+    n_launch = 0
+    for i in range(args.steps):
+        flush_l2(flush)
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+        n_launch += launches()
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t_wall
+    dist_barrier()
+    clk = clocks.stop()
+    dev_ms = sum(a.elapsed_time(b) for a, b in evs)
+    prof = profile_read()
+    st = status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} in the timed region")
+    max_ms = dist_max(dev_ms, dev)
+    all_units = dist_sum(units(spec, inp) * args.steps, dev)
+    value = all_units / (max_ms / 1e3)
+
+    # ---- end to end: pinned host inputs -> device, forward, result -> host
+    ins, outs = e2e_io()
+    host_in = {k: v.cpu().pin_memory() for k, v in ins.items()}
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    for it in range(e2e_steps + 1):
+        if it == 1:
+            dist_barrier()
+            torch.cuda.synchronize(dev)
+            ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ea.record(stream)
+        for k, v in host_in.items():
+            ins[k].copy_(v, non_blocking=True)
+        step()
+        for o, h in zip(outs, host_out):
+            h.copy_(o, non_blocking=True)
+    eb.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = dist_max(ea.elapsed_time(eb) / e2e_steps, dev)
+    e2e_value = dist_sum(units(spec, inp), dev) / (e2e_ms / 1e3)
+    st = status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} in the end-to-end loop")
+
+    peaks = load_peaks()
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 4),
+        "us_per_timestep": round(max_ms / args.steps * 1e3 / spec.T, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if getattr(spec, "dtype", "f32") == "bf16" else "f32",
+        "data": "synthetic",
+        "config": workload_config(spec, inp, ws),
+        "roofline": roofline(spec, inp, prof, peaks, nsm, dev_ms / args.steps),
+        "path_roofline": path_roofline(spec, inp, peaks, nsm, max_ms / args.steps),
+        "kernels": {k: {"ms_total": round(v[0], 3), "launches": v[1]} for k, v in prof.items()}
+        if prof else None,
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": n_launch,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    return line, inp
+
+
+def path_roofline(spec, inp, peaks, nsm, ms_step):
+    """Whole-step roofline: max(FLOPs / peak(dtype), compulsory bytes / HBM)."""
+    fl = total_flops(spec, inp)
+    if getattr(spec, "dtype", "f32") == "bf16":
+        peak = peaks["bf16_tflops_sustained"] * 1e12
+    else:
+        peak = fp32_alu_peak_tflops(nsm, peaks["sm_max_mhz"]) * 1e12
+    t_flop = fl / peak
+    byt = compulsory_bytes(spec, inp)
+    t_byte = byt / (peaks["hbm_gbs"] * 1e9)
+    t_roof = max(t_flop, t_byte)
+    return {"flop": fl, "compulsory_bytes": byt, "roofline_ms": round(t_roof * 1e3, 4),
+            "frac": round(t_roof * 1e3 / ms_step, 5)}
+
+
+def compulsory_bytes(spec, inp) -> int:
+    if isinstance(spec, wl.RssmSpec):
+        S, A, Hd, RH = spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden
+        w = Hd * (S + A + 1) + 3 * RH * (Hd + RH + 2) + Hd * (RH + 1) + 2 * S * (Hd + 1)
+        io = spec.T * spec.B * (A + S + 3 * S + RH)
+        return 4 * (w + io)
+    es = 2 if spec.dtype == "bf16" else 4
+    D, nG, H, Ho = spec.D, spec.nG, spec.hidden, spec.Hout
+    w = 0
+    for layer in range(spec.layers):
+        K = spec.in_dim if layer == 0 else D * Ho
+        w += D * (nG * H * (K + Ho) * es + 2 * nG * H * 4 + (spec.proj * H * es if spec.proj else 0))
+    M = active_rows(spec, inp)
+    x = M * spec.in_dim * 4
+    y = spec.T * spec.B * D * Ho * 4
+    st = spec.layers * D * spec.B * (Ho + (H if spec.cell == "lstm" else 0)) * 4
+    h0 = st if (inp.get("h0") is not None) else 0
+    return w + x + y + st + h0
+
+
+def workload_config(spec, inp, ws):
+    c = {"workload": spec.name, "T": spec.T, "B": spec.B, "replicas": ws,
+         "l2": "inputs larger than L2" if input_bytes(spec, inp) > L2_BYTES
+         else "L2 flushed between timed steps (256 MB write)"}
+    if isinstance(spec, wl.RssmSpec):
+        c.update(state_dim=spec.state_dim, action_dim=spec.action_dim, hidden=spec.hidden,
+                 rnn_hidden=spec.rnn_hidden)
+    else:
+        c.update(cell=spec.cell, layers=spec.layers, in_dim=spec.in_dim, hidden=spec.hidden,
+                 proj=spec.proj, bidirectional=spec.bidir,
+                 varlen=None if inp.get("lengths") is None else
+                 {"sum_len": int(inp["lengths"].sum()), "range": list(spec.varlen)})
+    c["l2_flush_each_step"] = True
+    return c
+
+
+def input_bytes(spec, inp):
+    if isinstance(spec, wl.RssmSpec):
+        return inp["actions"].numel() * 4 + inp["eps"].numel() * 4
+    return inp["x"].numel() * 4
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample(spec, inp, rows, threads):
+    import oracle
+    t0 = time.perf_counter()
+    if isinstance(spec, wl.RssmSpec):
+        oracle.rssm_unroll(inp["weights"], inp["actions"], inp["eps"], state0=inp["state0"],
+                           belief0=inp["belief0"], rows=rows, threads=threads)
+    else:
+        oracle.rnn_forward(oracle.LSTM if spec.cell == "lstm" else oracle.GRU, inp["x"],
+                           inp["weights"], hidden=spec.hidden, proj=spec.proj,
+                           bidirectional=spec.bidir, lengths=inp["lengths"], h0=inp["h0"],
+                           c0=inp["c0"], bf16_weights=spec.dtype == "bf16", rows=rows,
+                           threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def sample_rows(spec, inp, cores, budget_s):
+    """Rows for a bounded oracle sample: at most one per core, at least one; when a
+    single row already exceeds the budget, one row."""
+    per_row = oracle_sample(spec, inp, [0], 1)
+    n = max(1, min(spec.B, cores, int(budget_s * cores / max(per_row, 1e-9))))
+    return list(range(n)), per_row
+
+
+def cpu_baseline(spec, inp, budget_s=20.0):
+    import oracle
+    oracle.build()
+    cores = cpu_cores()
+    rows, _ = sample_rows(spec, inp, cores, budget_s)
+    threads = min(cores, len(rows))
+    t = oracle_sample(spec, inp, rows, threads)
+    value = len(rows) * spec.T / t
+    return {"value": round(value, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{len(rows)} of {spec.B} batch rows, all {spec.T} steps and layers "
+                      f"(rows are independent), fp64, {threads} threads",
+            "seconds": round(t, 3)}
+
+
+def run_reference(args, spec):
+    import oracle
+    oracle.build()
+    inp = (wl.make_rssm_inputs(spec, seed=args.seed) if isinstance(spec, wl.RssmSpec)
+           else wl.make_rnn_inputs(spec, seed=args.seed))
+    cores = cpu_cores()
+    # size each step so that warm-up + timed steps stay within ~3 minutes
+    budget = max(1.0, min(20.0, 180.0 / max(1, args.steps + args.warmup)))
+    rows, _ = sample_rows(spec, inp, cores, budget)
+    threads = min(cores, len(rows))
+    for _ in range(args.warmup):
+        oracle_sample(spec, inp, rows, threads)
+    t = 0.0
+    for _ in range(args.steps):
+        t += oracle_sample(spec, inp, rows, threads)
+    value = len(rows) * spec.T * args.steps / t
+    sample = (f"{len(rows)} of {spec.B} batch rows per step, all {spec.T} steps and layers, "
+              f"fp64, {threads} threads")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(spec, inp, 1),
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------- main
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gru", choices=sorted(WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--T", type=int, default=0,
+                    help="override the sequence length (small cases for profiler captures)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    spec = WORKLOADS[args.workload]
+    if args.T > 0:
+        kw = {"T": args.T, "name": f"{spec.name}@T{args.T}"}
+        if getattr(spec, "varlen", None) is not None:
+            kw["varlen"] = (min(spec.varlen[0], args.T), args.T)
+        spec = spec.scaled(**kw)
+    rank, local, ws = dist_info()
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, spec)), flush=True)
+        return 0
+
+    rank, local, ws = dist_init("nccl")
+    line, inp = run_ours(args, spec, rank, local, ws)
+    if rank == 0:
+        if ws == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(spec, inp, args.cpu_budget)
+        else:
+            line["cpu_baseline"] = None
+        print(json.dumps(line), flush=True)
+    if torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

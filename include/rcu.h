@@ -73,6 +73,9 @@ typedef struct rcu_rssm_s *rcu_rssm_t;
                                          first step barrier, so the wait must time out */
 #define RCU_ATTR_FORCE_PATH 3         /* 0 = automatic, 1 = portable SIMT kernels only,
                                          2 = tensor-core (tcgen05) kernels where supported */
+#define RCU_ATTR_PROFILE 4            /* 1 = record a CUDA event pair around every kernel
+                                         this handle launches (on the launching stream);
+                                         read the totals with rnn_profile_entry */
 
 /* Message of the last failure on this host thread ("" if none). */
 RCU_API const char *rcu_last_error(void);
@@ -157,6 +160,16 @@ RCU_API int rnn_set_attr(rcu_rnn_t h, int attr, int64_t value);
 
 /* Number of kernel launches the last rnn_forward enqueued. */
 RCU_API int rnn_last_launch_count(rcu_rnn_t h);
+
+/*
+ * Per-kernel timing collected while RCU_ATTR_PROFILE is on: entry i (0-based)
+ * gives the kernel's name, the summed event-measured duration in ms and the
+ * number of launches.  Synchronises on the recorded events.  Returns
+ * RCU_ERR_INVALID past the last entry.  rnn_profile_reset clears the totals.
+ */
+RCU_API int rnn_profile_entry(rcu_rnn_t h, int i, const char **name, double *total_ms,
+                              int64_t *count);
+RCU_API int rnn_profile_reset(rcu_rnn_t h);
 
 /* Free the handle, its weights and workspace (synchronises the device). */
 RCU_API int rnn_destroy(rcu_rnn_t h);

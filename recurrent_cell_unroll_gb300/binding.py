@@ -27,10 +27,12 @@ RCU_F32, RCU_BF16 = 0, 1
 RCU_OK, RCU_ERR_INVALID, RCU_ERR_UNSUPPORTED, RCU_ERR_CUDA = 0, -1, -2, -3
 RCU_ERR_TIMEOUT, RCU_ERR_LENGTHS, RCU_ERR_STATE = -4, -5, -6
 RCU_ATTR_BARRIER_TIMEOUT_NS, RCU_ATTR_TEST_DROP_ARRIVAL, RCU_ATTR_FORCE_PATH = 1, 2, 3
+RCU_ATTR_PROFILE = 4
 
 EXPORTED = (
     "rcu_last_error", "rcu_version", "rnn_create", "rnn_set_weights", "rnn_forward",
     "rnn_get_pack", "rnn_get_status", "rnn_set_attr", "rnn_last_launch_count", "rnn_destroy",
+    "rnn_profile_entry", "rnn_profile_reset",
     "rssm_create", "rssm_set_weights", "rssm_unroll", "rssm_get_status",
     "rssm_last_launch_count", "rssm_destroy",
 )
@@ -72,6 +74,9 @@ def load(path: Optional[str] = None):
             "rnn_set_attr": (I, [P, I, I64]),
             "rnn_last_launch_count": (I, [P]),
             "rnn_destroy": (I, [P]),
+            "rnn_profile_entry": (I, [P, I, ctypes.POINTER(ctypes.c_char_p),
+                                      ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64)]),
+            "rnn_profile_reset": (I, [P]),
             "rssm_create": (I, [ctypes.POINTER(P), I, I, I, I]),
             "rssm_set_weights": (I, [P] + [P] * 10 + [P]),
             "rssm_unroll": (I, [P, I, I] + [P] * 8 + [P]),
@@ -177,6 +182,19 @@ def rnn_last_launch_count(h) -> int:
     return load().rnn_last_launch_count(h)
 
 
+def rnn_profile_entry(h, i: int):
+    """(name, total_ms, launches) of profile entry i, or None past the end."""
+    name, ms, n = ctypes.c_char_p(), ctypes.c_double(), ctypes.c_int64()
+    rc = load().rnn_profile_entry(h, i, ctypes.byref(name), ctypes.byref(ms), ctypes.byref(n))
+    if rc != RCU_OK:
+        return None
+    return name.value.decode(), ms.value, n.value
+
+
+def rnn_profile_reset(h):
+    _check(load().rnn_profile_reset(h))
+
+
 def rnn_destroy(h):
     if h:
         load().rnn_destroy(h)
@@ -259,6 +277,16 @@ class RNN:
 
     def launch_count(self) -> int:
         return rnn_last_launch_count(self.h)
+
+    def profile(self) -> dict:
+        """{kernel name: (total_ms, launches)} recorded while RCU_ATTR_PROFILE is on."""
+        out, i = {}, 0
+        while True:
+            e = rnn_profile_entry(self.h, i)
+            if e is None:
+                return out
+            out[e[0]] = (e[1], e[2])
+            i += 1
 
     def close(self):
         if self.h:

@@ -116,6 +116,52 @@ struct rcu_rnn_s {
   int force_path = 0;
   int launches = 0;
   bool used_tc_gemm = false, used_tc_rec = false;
+  // opt-in per-kernel timing with CUDA events on the launching stream
+  bool profile = false;
+  struct Pending { const char *name; cudaEvent_t a, b; };
+  std::vector<Pending> pending;
+  std::vector<cudaEvent_t> pool;
+  std::vector<std::pair<std::string, std::pair<double, long>>> totals;
+  const char *open_name = nullptr;
+  cudaEvent_t open_ev = nullptr;
+  cudaEvent_t get_event() {
+    if (!pool.empty()) { cudaEvent_t e = pool.back(); pool.pop_back(); return e; }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+  void begin(const char *name, cudaStream_t s) {
+    if (!profile) return;
+    open_name = name;
+    open_ev = get_event();
+    cudaEventRecord(open_ev, s);
+  }
+  void end(cudaStream_t s) {
+    ++launches;
+    if (!profile || !open_ev) return;
+    cudaEvent_t b = get_event();
+    cudaEventRecord(b, s);
+    pending.push_back({open_name, open_ev, b});
+    open_ev = nullptr;
+  }
+  void collect() {
+    for (auto &p : pending) {
+      cudaEventSynchronize(p.b);
+      float ms = 0.f;
+      cudaEventElapsedTime(&ms, p.a, p.b);
+      bool found = false;
+      for (auto &t : totals)
+        if (t.first == p.name) { t.second.first += ms; t.second.second += 1; found = true; break; }
+      if (!found) totals.push_back({p.name, {ms, 1L}});
+      pool.push_back(p.a);
+      pool.push_back(p.b);
+    }
+    pending.clear();
+  }
+  ~rcu_rnn_s() {
+    for (auto &p : pending) { cudaEventDestroy(p.a); cudaEventDestroy(p.b); }
+    for (auto e : pool) cudaEventDestroy(e);
+  }
 };
 
 static size_t esize(int dtype) { return dtype == RCU_BF16 ? 2 : 4; }
@@ -197,6 +243,9 @@ extern "C" int rnn_set_attr(rcu_rnn_t h, int attr, int64_t value) {
       h->timeout_ns = value;
       return RCU_OK;
     case RCU_ATTR_TEST_DROP_ARRIVAL: h->drop_arrival = value != 0; return RCU_OK;
+    case RCU_ATTR_PROFILE:
+      h->profile = value != 0;
+      return RCU_OK;
     case RCU_ATTR_FORCE_PATH:
       if (value < 0 || value > 2) return fail(RCU_ERR_INVALID, "force_path must be 0, 1 or 2");
       h->force_path = (int)value;
@@ -372,11 +421,13 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
   CU(cudaMemsetAsync(h->ctl.p, 0, ctl_bytes(h->layers), s));
   CU(cudaMemsetAsync(h->hx, 0, (size_t)D * 2 * B * h->Kp * es, s));
   if (h->P > 0) CU(cudaMemsetAsync(h->mx, 0, (size_t)D * B * h->Hp * es, s));
+  h->begin("meta_sort", s);
   CU(launch_meta(lengths, B, T, h->meta, err, s));
-  h->launches++;
+  h->end(s);
   if (varlen) {
+    h->begin("zero_tail", s);
     CU(launch_zero_tail(y, lengths, T, B, D * Hout, err, s));
-    h->launches++;
+    h->end(s);
   }
 
   // layer-0 GEMM operand
@@ -386,12 +437,13 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
   const int Mmax = T * B;
   if (varlen || bf) {
     ldx = round_up(h->in_dim, 8);
+    h->begin("pack_rows", s);
     if (bf)
       CU(launch_pack_rows<__nv_bfloat16>(x, T, B, h->in_dim, h->meta, (__nv_bfloat16 *)h->xp,
                                          ldx, s));
     else
       CU(launch_pack_rows<float>(x, T, B, h->in_dim, h->meta, (float *)h->xp, ldx, s));
-    h->launches++;
+    h->end(s);
     X = h->xp;
   }
   h->used_tc_gemm = h->used_tc_rec = false;
@@ -400,7 +452,9 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
     const int ldw = round_up(K, 8);
     float *G = (float *)h->g;
     bool done = false;
-    if (bf && h->force_path != 1 && tc_gemm_supported(K, N)) {
+    const bool tc_gemm = bf && h->force_path != 1 && tc_gemm_supported(K, N);
+    h->begin(tc_gemm ? "input_gemm_tc" : "input_gemm_simt", s);
+    if (tc_gemm) {
       cudaError_t e = launch_tc_gemm((const __nv_bfloat16 *)X, ldx, (const __nv_bfloat16 *)h->wih[l].p,
                                      ldw, (const float *)h->gbias[l].p, G, N, Mmax, M_dev, N, K,
                                      h->nsm, s);
@@ -418,7 +472,7 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
                                                           Mmax, M_dev, N, K, s);
       if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "gemm: %s", cudaGetErrorString(e));
     }
-    h->launches++;
+    h->end(s);
 
     const bool last = l == h->layers - 1;
     RecParams p{};
@@ -446,8 +500,11 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
     p.timeout_ns = (uint64_t)h->timeout_ns;
     p.drop_arrival = h->drop_arrival && l == 0;
     bool rec_done = false;
-    if (bf && h->force_path != 1 && tc_rec_supported(h->cell, H, Hout, h->P, h->nsm) &&
-        h->lw[(size_t)l * D].tc_whh.p) {
+    const bool tc_rec = bf && h->force_path != 1 &&
+                        tc_rec_supported(h->cell, H, Hout, h->P, h->nsm) &&
+                        h->lw[(size_t)l * D].tc_whh.p;
+    h->begin(tc_rec ? "recurrent_tc" : "recurrent_simt", s);
+    if (tc_rec) {
       TcRecParams tp;
       tp.base = p;
       for (int d = 0; d < D; ++d) tp.Wtc[d] = h->lw[(size_t)l * D + d].tc_whh.p;
@@ -471,7 +528,7 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
       if (e != cudaSuccess)
         return fail(RCU_ERR_CUDA, "recurrent kernel launch: %s", cudaGetErrorString(e));
     }
-    h->launches++;
+    h->end(s);
     // next layer reads this layer's packed output
     X = h->ymid;
     ldx = D * Hout;
@@ -516,6 +573,24 @@ extern "C" int rnn_get_status(rcu_rnn_t h, void *stream) {
 }
 
 extern "C" int rnn_last_launch_count(rcu_rnn_t h) { return h ? h->launches : -1; }
+
+extern "C" int rnn_profile_entry(rcu_rnn_t h, int i, const char **name, double *total_ms,
+                                 int64_t *count) {
+  if (!h) return fail(RCU_ERR_INVALID, "rnn_profile_entry: NULL handle");
+  h->collect();
+  if (i < 0 || i >= (int)h->totals.size()) return fail(RCU_ERR_INVALID, "no profile entry %d", i);
+  if (name) *name = h->totals[i].first.c_str();
+  if (total_ms) *total_ms = h->totals[i].second.first;
+  if (count) *count = h->totals[i].second.second;
+  return RCU_OK;
+}
+
+extern "C" int rnn_profile_reset(rcu_rnn_t h) {
+  if (!h) return fail(RCU_ERR_INVALID, "rnn_profile_reset: NULL handle");
+  h->collect();
+  h->totals.clear();
+  return RCU_OK;
+}
 
 extern "C" int rnn_destroy(rcu_rnn_t h) {
   if (!h) return RCU_OK;
