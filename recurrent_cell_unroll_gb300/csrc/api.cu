@@ -457,7 +457,7 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
     if (tc_gemm) {
       cudaError_t e = launch_tc_gemm((const __nv_bfloat16 *)X, ldx, (const __nv_bfloat16 *)h->wih[l].p,
                                      ldw, (const float *)h->gbias[l].p, G, N, Mmax, M_dev, N, K,
-                                     h->nsm, s);
+                                     h->nsm, s, err, (uint64_t)h->timeout_ns);
       if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "tc gemm: %s", cudaGetErrorString(e));
       done = true;
       h->used_tc_gemm = true;

@@ -16,7 +16,7 @@ namespace rcu {
 bool tc_gemm_supported(int K, int N);
 cudaError_t launch_tc_gemm(const __nv_bfloat16 *X, int ldx, const __nv_bfloat16 *W, int ldw,
                            const float *bias, float *G, int ldg, int M, const int32_t *M_dev,
-                           int N, int K, int nsm, cudaStream_t s);
+                           int N, int K, int nsm, cudaStream_t s, int *err, uint64_t timeout_ns);
 
 // ---- recurrent_tc.cu: persistent recurrent kernel with the per-step
 // h W_hh^T on tcgen05.
