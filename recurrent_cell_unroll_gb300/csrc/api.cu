@@ -339,7 +339,7 @@ extern "C" int rnn_set_weights(rcu_rnn_t h, int layer, int dir, const float *W_i
     CU(lw.bhn.upload(bn.data(), bn.size() * sizeof(float)));
   }
   // --- tensor-core layout (bf16 path only)
-  if (bf && tc_rec_supported(h->cell, H, Hout, P, h->nsm)) {
+  if (bf && tc_rec_packable(h->cell, H, Hout, P)) {
     std::vector<uint16_t> packed;
     tc_pack_whh(h->cell, H, Hout, whh.data(), packed, f2bf);
     CU(lw.tc_whh.upload(packed.data(), packed.size() * 2));
@@ -415,10 +415,14 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
   const int D = h->D, H = h->H, Hout = h->Hout, nG = h->nG;
   const int N = D * nG * H;
   const bool varlen = lengths != nullptr;
+  // control block: error word, then per layer `cstride` barrier counters
+  const int cstride = std::max(4, tc_rec_counters(B, D));
+  const size_t cbytes = 64 + (size_t)h->layers * cstride * 4 + 64;
+  CU(h->ctl.ensure(std::max(cbytes, ctl_bytes(h->layers))));
   int *err = (int *)h->ctl.p;
   unsigned *ctr = (unsigned *)((char *)h->ctl.p + 64);
 
-  CU(cudaMemsetAsync(h->ctl.p, 0, ctl_bytes(h->layers), s));
+  CU(cudaMemsetAsync(h->ctl.p, 0, std::max(cbytes, ctl_bytes(h->layers)), s));
   CU(cudaMemsetAsync(h->hx, 0, (size_t)D * 2 * B * h->Kp * es, s));
   if (h->P > 0) CU(cudaMemsetAsync(h->mx, 0, (size_t)D * B * h->Hp * es, s));
   h->begin("meta_sort", s);
@@ -452,7 +456,8 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
     const int ldw = round_up(K, 8);
     float *G = (float *)h->g;
     bool done = false;
-    const bool tc_gemm = bf && h->force_path != 1 && tc_gemm_supported(K, N);
+    // TMA needs 16-byte row strides: the tensor-core GEMM takes rows of a multiple of 8
+    const bool tc_gemm = bf && h->force_path != 1 && (ldx % 8) == 0 && tc_gemm_supported(K, N);
     h->begin(tc_gemm ? "input_gemm_tc" : "input_gemm_simt", s);
     if (tc_gemm) {
       cudaError_t e = launch_tc_gemm((const __nv_bfloat16 *)X, ldx, (const __nv_bfloat16 *)h->wih[l].p,
@@ -495,13 +500,13 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
     p.y = last ? y : nullptr;
     p.ymid = last ? nullptr : h->ymid;
     p.hx = h->hx; p.mx = h->mx; p.hst = h->hst; p.cst = h->cst;
-    p.ctr = ctr + 4 * l;  // fresh counters per layer (zeroed above)
+    p.ctr = ctr + (size_t)cstride * l;  // fresh counters per layer (zeroed above)
     p.err = err;
     p.timeout_ns = (uint64_t)h->timeout_ns;
     p.drop_arrival = h->drop_arrival && l == 0;
     bool rec_done = false;
     const bool tc_rec = bf && h->force_path != 1 &&
-                        tc_rec_supported(h->cell, H, Hout, h->P, h->nsm) &&
+                        tc_rec_supported(h->cell, H, Hout, h->P, h->nsm, B, D) &&
                         h->lw[(size_t)l * D].tc_whh.p;
     h->begin(tc_rec ? "recurrent_tc" : "recurrent_simt", s);
     if (tc_rec) {

@@ -38,7 +38,7 @@ constexpr size_t SMEM_BYTES =
 constexpr uint32_t TMEM_COLS = 512;
 
 struct Bars {
-  uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2];
+  uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], mdone;
   uint32_t tmem_base;
   int abort;
 };
@@ -72,6 +72,7 @@ __global__ void __launch_bounds__(NT, 1)
       tc::mbar_init(&bars->tfull[b], 1);
       tc::mbar_init(&bars->tempty[b], EPI_WARPS);
     }
+    tc::mbar_init(&bars->mdone, 1);
     bars->abort = 0;
     tc::fence_mbar_init();
   }
@@ -167,6 +168,12 @@ __global__ void __launch_bounds__(NT, 1)
     }
   }
 done:
+  if (warp == 1 && lane == 0) {
+    // drain: every MMA issued completes before TMEM is released
+    tc::mma_commit(&bars->mdone);
+    volatile int never = 0;
+    tc::mbar_wait(&bars->mdone, 0, nullptr, &never, 100000000ull);
+  }
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 1) {

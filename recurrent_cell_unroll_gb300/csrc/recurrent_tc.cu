@@ -1,9 +1,457 @@
-// placeholder: replaced by the tcgen05 recurrent kernel
+// Persistent recurrent kernel on the 5th-generation tensor cores (bf16 path).
+//
+// One cooperative launch runs every timestep of one layer.  CTA (d, bg, ug)
+// owns direction d, batch rows [bg*128, bg*128+128) (sorted order) and
+// hidden units [ug*16, ug*16+16).  Per step it computes
+//     R[b, n] = sum_k h_{t-1}[b, k] * W_hh[row(n), k]
+// with tcgen05.mma (M = 128 batch rows, N = 16 units x gates, K = Hout),
+//   - B operand: the CTA's W_hh rows (all gates of its 16 units), loaded once
+//     by TMA and resident in shared memory for the whole sequence;
+//   - A operand: h_{t-1} of the batch group, bf16, streamed from the L2-
+//     resident exchange buffer by TMA through a ring of 16 KB stages;
+//   - D: 128 TMEM lanes x N fp32 columns.
+// Four epilogue warps (thread = batch row = TMEM lane) keep h and c of their
+// row's 16 units in registers for the whole sequence, add the precomputed
+// input projection G, apply the gates (LSTM: sigmoid/tanh, c update; GRU:
+// r, z, n with the reset gate on the hidden-side n pre-activation incl. its
+// bias), and write h_t (bf16 exchange buffer, output).  A bounded
+// release/acquire counter over the CTAs of (d, bg) crosses each step.
+// This is the "recurrent hidden-hidden dense" of "[TOPI] TE implementation of
+// LSTM using scan" (apache/tvm PR 11531) with the gate and activation math
+// inlined, as that page's benchmark did.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
 #include "tc.h"
+#include "tc_common.cuh"
+
 namespace rcu {
-bool tc_rec_supported(int, int, int, int, int) { return false; }
-void tc_pack_whh(int, int, int, const float *, std::vector<uint16_t> &out, uint16_t (*)(float)) {
-  out.clear();
+
+namespace {
+
+constexpr int UNITS = 16;       // hidden units per CTA
+constexpr int BG = 128;         // batch rows per CTA (MMA M)
+constexpr int BK = 64;          // K per stage (128 bytes of bf16)
+constexpr int A_STAGE = BG * BK * 2;
+constexpr int NT = 192;         // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int SMEM_LIMIT = 227 * 1024;
+constexpr int MAX_STAGES = 8;
+
+struct Maps {
+  CUtensorMap hx;    // [D*2*B rows][K cols], ld Kp, bf16, box 64 x 128
+  CUtensorMap w[2];  // per direction [NU*N rows][K cols], ld Kp, bf16, box 64 x N
+};
+
+struct Ctl {
+  uint64_t full[MAX_STAGES], empty[MAX_STAGES], wbar, tfull, tfree, mdone;
+  uint32_t tmem_base;
+  int abort;
+  int go;  // epilogue: result of the per-step accumulator wait, shared by all 128 threads
+};
+
+struct Geo {
+  int N, nkb, stages;
+  size_t w_bytes, smem;
+};
+
+__host__ __device__ inline Geo make_geo(int nG, int K) {
+  Geo g;
+  g.N = nG * UNITS;
+  g.nkb = ceil_div(K, BK);
+  g.w_bytes = (size_t)g.nkb * g.N * 128;
+  const size_t fixed = 1024 + g.w_bytes + 256;
+  int st = (int)((SMEM_LIMIT - (long long)fixed) / A_STAGE);
+  g.stages = st > MAX_STAGES ? MAX_STAGES : st;
+  g.smem = fixed + (size_t)(g.stages > 0 ? g.stages : 0) * A_STAGE;
+  return g;
 }
-cudaError_t launch_tc_recurrent(const TcRecParams &, int, cudaStream_t) { return cudaErrorNotSupported; }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void load16(const float *p, float (&v)[16]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 f = __ldg(reinterpret_cast<const float4 *>(p) + i);
+    v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+  }
+}
+
+template <int NG>
+__global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ Maps maps,
+                                                       const RecParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  const Geo geo = make_geo(NG, p.Hout);
+  const int N = geo.N, nkb = geo.nkb, STG = geo.stages;
+  uint8_t *sW = smem;                       // resident B operand, nkb blocks of N x 128 B
+  uint8_t *sA = smem + geo.w_bytes;         // ring of STG stages of 128 x 128 B
+  Ctl *ctl = reinterpret_cast<Ctl *>(sA + (size_t)STG * A_STAGE);
+
+  const int NU = p.NU, NBG = ceil_div(p.B, BG);
+  const int d = blockIdx.x / (NBG * NU);
+  const int rem = blockIdx.x % (NBG * NU);
+  const int bg = rem / NU, ug = rem % NU;
+  const int u0 = ug * UNITS, row0 = bg * BG;
+  const int B = p.B, H = p.H, Kp = p.Kp;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  volatile int *abort = &ctl->abort;
+  const uint64_t tmo = p.timeout_ns;
+  unsigned *ctr = p.ctr + d * NBG + bg;
+  // steps this batch group runs: the longest row of the group (rows sorted by length)
+  const int Tg = row0 < B ? p.meta.lens_sorted[row0] : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STG; ++s) {
+      tc::mbar_init(&ctl->full[s], 1);
+      tc::mbar_init(&ctl->empty[s], 1);
+    }
+    tc::mbar_init(&ctl->wbar, 1);
+    tc::mbar_init(&ctl->tfull, 1);
+    tc::mbar_init(&ctl->tfree, 4);
+    tc::mbar_init(&ctl->mdone, 1);
+    ctl->abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) tc::tmem_alloc(&ctl->tmem_base, 64);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tbase = ctl->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tc::prefetch_tmap(&maps.hx);
+      tc::prefetch_tmap(&maps.w[d]);
+      // resident weights: rows [ug*N, ug*N + N) of this direction's packed W_hh
+      tc::mbar_arrive_expect_tx(&ctl->wbar, (uint32_t)geo.w_bytes);
+      for (int kb = 0; kb < nkb; ++kb)
+        tc::tma_load_2d(sW + (size_t)kb * N * 128, &maps.w[d], &ctl->wbar, kb * BK, ug * N);
+      int stage = 0;
+      uint32_t phase = 0;
+      int pend_stage[MAX_STAGES], npend = 0;
+      uint32_t pend_phase[MAX_STAGES];
+      for (int step = 0; step < Tg; ++step) {
+        // wait until every CTA of (d, bg) has published h_{step-1}
+        const unsigned target = (unsigned)(NU * (step + 1));
+        if (ld_acquire_gpu(ctr) < target) {
+          const uint64_t deadline = globaltimer_ns() + tmo;
+          uint32_t spins = 0;
+          bool ok = true;
+          while (ld_acquire_gpu(ctr) < target) {
+            if ((++spins & 63u) == 0) {
+              if (*abort || ld_volatile_int(p.err) != DEV_OK) { ok = false; break; }
+              if (globaltimer_ns() > deadline) {
+                atomicCAS(p.err, DEV_OK, DEV_TIMEOUT);
+                ok = false;
+                break;
+              }
+            }
+          }
+          if (!ok) { *abort = 1; break; }
+        }
+        fence_proxy_async_global();
+        const int arow = (d * 2 + (step & 1)) * B + row0;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!tc::mbar_wait(&ctl->empty[stage], phase ^ 1, p.err, abort, tmo)) goto producer_out;
+          tc::mbar_arrive_expect_tx(&ctl->full[stage], A_STAGE);
+          tc::tma_load_2d(sA + (size_t)stage * A_STAGE, &maps.hx, &ctl->full[stage], kb * BK, arow);
+          pend_stage[npend % MAX_STAGES] = stage;
+          pend_phase[npend % MAX_STAGES] = phase;
+          ++npend;
+          if (++stage == STG) { stage = 0; phase ^= 1; }
+        }
+      }
+    producer_out:
+      if (*abort) {
+        // let the copies already issued land before the CTA leaves (bounded
+        // waits that ignore the abort flag)
+        volatile int never = 0;
+        tc::mbar_wait(&ctl->wbar, 0, nullptr, &never, 100000000ull);
+        const int n = npend < STG ? npend : STG;
+        for (int i = 0; i < n; ++i) {
+          const int k = (npend - 1 - i) % MAX_STAGES;
+          tc::mbar_wait(&ctl->full[pend_stage[k]], pend_phase[k], nullptr, &never, 100000000ull);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(BG, NG * UNITS);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = tc::mbar_wait(&ctl->wbar, 0, p.err, abort, tmo);
+      for (int step = 0; ok && step < Tg; ++step) {
+        if (!tc::mbar_wait(&ctl->tfree, (step & 1) ^ 1, p.err, abort, tmo)) break;
+        tc::tc_fence_after();
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!tc::mbar_wait(&ctl->full[stage], phase, p.err, abort, tmo)) { ok = false; break; }
+          tc::tc_fence_after();
+          const uint32_t a0 = tc::smem_u32(sA + (size_t)stage * A_STAGE);
+          const uint32_t b0 = tc::smem_u32(sW + (size_t)kb * N * 128);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc::mma_bf16(tbase, tc::smem_desc_sw128(a0 + kk * 32),
+                         tc::smem_desc_sw128(b0 + kk * 32), idesc, (kb | kk) != 0);
+          tc::mma_commit(&ctl->empty[stage]);
+          if (++stage == STG) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc::mma_commit(&ctl->tfull);
+      }
+      // drain: every MMA issued above completes before TMEM is released
+      tc::mma_commit(&ctl->mdone);
+      volatile int never = 0;
+      tc::mbar_wait(&ctl->mdone, 0, nullptr, &never, 100000000ull);
+    }
+  } else {
+    // ---------------- epilogue: thread = batch row r (TMEM lane r)
+    const int q = warp % 4;
+    const int r = q * 32 + lane;
+    const int s = row0 + r;
+    const bool row_ok = s < B;
+    const int ldo = p.D * p.Hout;
+    const int Kp_ = Kp;
+    __nv_bfloat16 *hx = reinterpret_cast<__nv_bfloat16 *>(p.hx) + (size_t)d * 2 * B * Kp_;
+    const float *bhn = p.bhn[d];
+    const int nu = min(UNITS, H - u0);  // valid units of this CTA (UNITS unless H % 16)
+    // 16-byte vector access only where every address is 16-byte aligned
+    const bool vec_g = nu == UNITS && (H & 3) == 0;
+    const bool vec_y = nu == UNITS && (p.Hout & 3) == 0 &&
+                       (reinterpret_cast<uintptr_t>(p.y) & 15) == 0;
+    float h[UNITS], c[UNITS], bn[UNITS];
+    int b = 0, len = 0;
+    if (row_ok) {
+      b = p.meta.sorted_idx[s];
+      len = p.meta.lens_sorted[s];
+    }
+#pragma unroll
+    for (int j = 0; j < UNITS; ++j) {
+      const bool uj = row_ok && j < nu;
+      h[j] = (uj && p.h0) ? p.h0[((size_t)d * B + b) * p.Hout + u0 + j] : 0.f;
+      c[j] = (uj && p.c0 && NG == 4) ? p.c0[((size_t)d * B + b) * H + u0 + j] : 0.f;
+      bn[j] = (NG == 3 && bhn && j < nu) ? bhn[u0 + j] : 0.f;
+    }
+    if (row_ok) {
+      __nv_bfloat16 *dst = hx + (size_t)s * Kp_ + u0;
+#pragma unroll
+      for (int j = 0; j < UNITS; ++j)
+        if (j < nu) dst[j] = __float2bfloat16_rn(h[j]);
+    }
+    fence_proxy_async_global();
+    epi_bar();
+    if (threadIdx.x == 64) {
+      __threadfence();
+      red_release_gpu_add(ctr, (p.drop_arrival && blockIdx.x == 0) ? 0u : 1u);
+    }
+    for (int step = 0; step < Tg; ++step) {
+      const bool active = row_ok && step < len;
+      const int tt = d == 0 ? step : len - 1 - step;
+      float gx[NG][UNITS];
+      if (active) {
+        const size_t grow = (size_t)p.meta.step_off[tt] + s;
+        const float *gp = p.G + grow * p.ldG + (size_t)d * NG * H + u0;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          if (vec_g) {
+            load16(gp + (size_t)g * H, gx[g]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < UNITS; ++j) gx[g][j] = j < nu ? __ldg(gp + (size_t)g * H + j) : 0.f;
+          }
+        }
+      }
+      // one thread waits for the accumulator; the verdict is shared so that
+      // all 128 epilogue threads leave the loop together
+      if (threadIdx.x == 64) ctl->go = tc::mbar_wait(&ctl->tfull, step & 1, p.err, abort, tmo);
+      epi_bar();
+      if (!ctl->go) break;
+      tc::tc_fence_after();
+      float acc[NG][UNITS];
+#pragma unroll
+      for (int g = 0; g < NG; ++g)
+        tmem_ld16(tbase + (uint32_t)(g * UNITS) + ((uint32_t)(q * 32) << 16), acc[g]);
+      tc::tc_fence_before();
+      if (lane == 0) tc::mbar_arrive(&ctl->tfree);
+      if (active) {
+#pragma unroll
+        for (int j = 0; j < UNITS; ++j) {
+          if (NG == 4) {
+            const float ig = sigmoid_f(acc[0][j] + gx[0][j]);
+            const float fg = sigmoid_f(acc[1][j] + gx[1][j]);
+            const float gg = tanh_f(acc[2][j] + gx[2][j]);
+            const float og = sigmoid_f(acc[3][j] + gx[3][j]);
+            c[j] = fg * c[j] + ig * gg;
+            h[j] = og * tanh_f(c[j]);
+          } else {
+            const float rg = sigmoid_f(gx[0][j] + acc[0][j]);
+            const float zg = sigmoid_f(gx[1][j] + acc[1][j]);
+            const float ng = tanh_f(gx[2][j] + rg * (acc[NG - 1][j] + bn[j]));
+            h[j] = (1.f - zg) * ng + zg * h[j];
+          }
+        }
+        // exchange buffer for the next step (bf16 MMA operand)
+        __nv_bfloat16 *dst = hx + (size_t)(((step & 1) ^ 1) * B + s) * Kp_ + u0;
+        if (nu == UNITS) {
+          uint4 pk[2];
+          uint32_t *w = reinterpret_cast<uint32_t *>(pk);
+#pragma unroll
+          for (int j = 0; j < UNITS / 2; ++j) {
+            __nv_bfloat162 t2 = __floats2bfloat162_rn(h[2 * j], h[2 * j + 1]);
+            w[j] = *reinterpret_cast<uint32_t *>(&t2);
+          }
+          reinterpret_cast<uint4 *>(dst)[0] = pk[0];
+          reinterpret_cast<uint4 *>(dst)[1] = pk[1];
+        } else {
+#pragma unroll
+          for (int j = 0; j < UNITS; ++j)
+            if (j < nu) dst[j] = __float2bfloat16_rn(h[j]);
+        }
+        if (p.y) {
+          float *yo = p.y + ((size_t)tt * B + b) * ldo + (size_t)d * p.Hout + u0;
+          if (vec_y) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              reinterpret_cast<float4 *>(yo)[i] =
+                  make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < UNITS; ++j)
+              if (j < nu) yo[j] = h[j];
+          }
+        }
+        if (p.ymid) {
+          __nv_bfloat16 *ym = reinterpret_cast<__nv_bfloat16 *>(p.ymid) +
+                              ((size_t)p.meta.step_off[tt] + s) * ldo + (size_t)d * p.Hout + u0;
+#pragma unroll
+          for (int j = 0; j < UNITS; ++j)
+            if (j < nu) ym[j] = __float2bfloat16_rn(h[j]);
+        }
+      }
+      fence_proxy_async_global();
+      epi_bar();
+      if (threadIdx.x == 64) {
+        __threadfence();
+        red_release_gpu_add(ctr, 1u);
+      }
+    }
+    if (row_ok && !*abort) {
+#pragma unroll
+      for (int j = 0; j < UNITS; ++j) {
+        if (j >= nu) continue;
+        if (p.h_n) p.h_n[((size_t)d * B + b) * p.Hout + u0 + j] = h[j];
+        if (NG == 4 && p.c_n) p.c_n[((size_t)d * B + b) * H + u0 + j] = c[j];
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tbase, 64);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+bool make_map(CUtensorMap *map, const void *base, long long rows, int cols, int ld, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int tc_rec_units() { return UNITS; }
+
+bool tc_rec_packable(int cell, int H, int Hout, int P) {
+  if (P > 0) return false;  // projection runs on the portable kernel
+  if (H < 1 || Hout < 1) return false;
+  const int nG = cell == CELL_LSTM ? 4 : 3;
+  return make_geo(nG, Hout).stages >= 2 && encode_fn() != nullptr;
+}
+
+bool tc_rec_supported(int cell, int H, int Hout, int P, int nsm, int B, int D) {
+  if (!tc_rec_packable(cell, H, Hout, P)) return false;
+  const long long ctas = (long long)D * ceil_div(B, BG) * ceil_div(H, UNITS);
+  return ctas <= nsm;
+}
+
+int tc_rec_counters(int B, int D) { return D * ceil_div(B, BG); }
+
+void tc_pack_whh(int cell, int H, int Hout, const float *whh, std::vector<uint16_t> &out,
+                 uint16_t (*to_bf16)(float)) {
+  const int nG = cell == CELL_LSTM ? 4 : 3;
+  const int N = nG * UNITS, NU = ceil_div(H, UNITS), Kp = round_up(Hout, 8);
+  out.assign((size_t)NU * N * Kp, 0);
+  for (int ug = 0; ug < NU; ++ug)
+    for (int g = 0; g < nG; ++g)
+      for (int j = 0; j < UNITS; ++j) {
+        const int u = ug * UNITS + j;
+        if (u >= H) continue;
+        for (int k = 0; k < Hout; ++k)
+          out[((size_t)ug * N + g * UNITS + j) * Kp + k] = to_bf16(whh[(size_t)(g * H + u) * Hout + k]);
+      }
+}
+
+cudaError_t launch_tc_recurrent(const TcRecParams &tp, int nsm, cudaStream_t s) {
+  (void)nsm;
+  RecParams p = tp.base;
+  const int nG = p.nG;
+  const Geo geo = make_geo(nG, p.Hout);
+  p.NU = ceil_div(p.H, UNITS);
+  const int NBG = ceil_div(p.B, BG);
+  Maps maps;
+  if (!make_map(&maps.hx, p.hx, (long long)p.D * 2 * p.B, p.Hout, p.Kp, BG))
+    return cudaErrorInvalidValue;
+  for (int d = 0; d < 2; ++d) {
+    const void *w = tp.Wtc[d < p.D ? d : 0];
+    if (!make_map(&maps.w[d], w, (long long)p.NU * geo.N, p.Hout, p.Kp, geo.N))
+      return cudaErrorInvalidValue;
+  }
+  const void *fn = nG == 4 ? (const void *)rec_tc_kernel<4> : (const void *)rec_tc_kernel<3>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)geo.smem);
+  if (e != cudaSuccess) return e;
+  void *args[] = {&maps, &p};
+  return cudaLaunchCooperativeKernel(fn, dim3(p.D * NBG * p.NU), dim3(NT), args, geo.smem, s);
+}
+
 }  // namespace rcu

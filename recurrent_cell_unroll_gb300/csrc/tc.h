@@ -24,7 +24,12 @@ struct TcRecParams {
   RecParams base;
   const void *Wtc[2];  // tensor-core packed W_hh per direction (tc_pack_whh)
 };
-bool tc_rec_supported(int cell, int H, int Hout, int P, int nsm);
+// weights can be packed for the tensor-core kernel (shape only)
+bool tc_rec_packable(int cell, int H, int Hout, int P);
+// the kernel can run this forward (co-resident grid for B rows, D directions)
+bool tc_rec_supported(int cell, int H, int Hout, int P, int nsm, int B, int D);
+// barrier counters one layer needs
+int tc_rec_counters(int B, int D);
 void tc_pack_whh(int cell, int H, int Hout, const float *whh, std::vector<uint16_t> &out,
                  uint16_t (*to_bf16)(float));
 cudaError_t launch_tc_recurrent(const TcRecParams &p, int nsm, cudaStream_t s);

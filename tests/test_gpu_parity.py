@@ -81,6 +81,11 @@ SMALL = [
     wl.GRU_3L.scaled(dtype="f32", layers=2, bidir=True, T=9, B=5, in_dim=16, hidden=24,
                      varlen=(1, 9)),
     wl.GRU_3L.scaled(layers=1, T=5, B=1, in_dim=8, hidden=1024),
+    # tensor-core recurrent kernel: two batch groups with a ragged tail, ragged units
+    wl.LSTM_T80.scaled(name="lstm_bf16", dtype="bf16", layers=2, T=12, B=150, in_dim=40,
+                       hidden=70, h0_std=0.5, c0_std=0.5),
+    wl.GRU_3L.scaled(bidir=True, layers=2, T=15, B=140, in_dim=24, hidden=40, varlen=(1, 15)),
+    wl.GRU_3L.scaled(layers=1, T=9, B=256, in_dim=64, hidden=256),
 ]
 
 
@@ -214,6 +219,24 @@ def test_barrier_wait_times_out_and_context_survives():
     assert net.status() == 0
     ref = run_oracle(spec, inp)
     assert np.abs(y.cpu().numpy() - ref[0]).max() <= F32_TOL
+    net.close()
+
+
+def test_barrier_timeout_on_tensor_core_path():
+    spec = wl.GRU_3L.scaled(layers=1, T=4, B=20, in_dim=16, hidden=64)
+    inp = wl.make_rnn_inputs(spec, seed=14)
+    dev = torch.device("cuda")
+    net = binding.RNN.from_spec(spec)
+    net.set_weights(inp["weights"])
+    net.set_attr(binding.RCU_ATTR_BARRIER_TIMEOUT_NS, 50_000_000)
+    net.set_attr(binding.RCU_ATTR_TEST_DROP_ARRIVAL, 1)
+    net.forward(inp["x"].to(dev), h0=inp["h0"].to(dev))
+    assert net.status() == binding.RCU_ERR_TIMEOUT
+    net.set_attr(binding.RCU_ATTR_TEST_DROP_ARRIVAL, 0)
+    y, _, _ = net.forward(inp["x"].to(dev), h0=inp["h0"].to(dev))
+    assert net.status() == 0
+    ref = run_oracle(spec, inp)
+    assert _rel(y.cpu().numpy(), ref[0]) <= BF16_REL
     net.close()
 
 
