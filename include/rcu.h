@@ -73,6 +73,7 @@ typedef struct rcu_rssm_s *rcu_rssm_t;
                                          first step barrier, so the wait must time out */
 #define RCU_ATTR_FORCE_PATH 3         /* 0 = automatic, 1 = portable SIMT kernels only,
                                          2 = tensor-core (tcgen05) kernels where supported */
+#define RCU_ATTR_TRACE 5              /* 1 = record per-step timestamps (rnn_get_trace) */
 #define RCU_ATTR_PROFILE 4            /* 1 = record a CUDA event pair around every kernel
                                          this handle launches (on the launching stream);
                                          read the totals with rnn_profile_entry */
@@ -170,6 +171,17 @@ RCU_API int rnn_last_launch_count(rcu_rnn_t h);
 RCU_API int rnn_profile_entry(rcu_rnn_t h, int i, const char **name, double *total_ms,
                               int64_t *count);
 RCU_API int rnn_profile_reset(rcu_rnn_t h);
+
+/*
+ * Step trace of the first layer's recurrent kernel, recorded while
+ * RCU_ATTR_TRACE is on: for each step t < n_steps, 8 global-timer stamps (ns)
+ * of CTA 0 are copied to host_out[t*8 .. t*8+7] (0 where a slot is unused).
+ * Tensor-core kernel slots: 0 producer saw the step barrier, 1 first h stage
+ * landed, 2 last MMA issued, 3 epilogue got the accumulator, 4 epilogue
+ * published h_t.  Portable kernel slots: 0 step start, 1 gates done,
+ * 2 barrier passed.  Synchronises the stream.  host_out is host memory.
+ */
+RCU_API int rnn_get_trace(rcu_rnn_t h, int64_t *host_out, int n_steps, void *stream);
 
 /* Free the handle, its weights and workspace (synchronises the device). */
 RCU_API int rnn_destroy(rcu_rnn_t h);

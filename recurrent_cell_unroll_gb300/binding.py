@@ -27,12 +27,12 @@ RCU_F32, RCU_BF16 = 0, 1
 RCU_OK, RCU_ERR_INVALID, RCU_ERR_UNSUPPORTED, RCU_ERR_CUDA = 0, -1, -2, -3
 RCU_ERR_TIMEOUT, RCU_ERR_LENGTHS, RCU_ERR_STATE = -4, -5, -6
 RCU_ATTR_BARRIER_TIMEOUT_NS, RCU_ATTR_TEST_DROP_ARRIVAL, RCU_ATTR_FORCE_PATH = 1, 2, 3
-RCU_ATTR_PROFILE = 4
+RCU_ATTR_PROFILE, RCU_ATTR_TRACE = 4, 5
 
 EXPORTED = (
     "rcu_last_error", "rcu_version", "rnn_create", "rnn_set_weights", "rnn_forward",
     "rnn_get_pack", "rnn_get_status", "rnn_set_attr", "rnn_last_launch_count", "rnn_destroy",
-    "rnn_profile_entry", "rnn_profile_reset",
+    "rnn_profile_entry", "rnn_profile_reset", "rnn_get_trace",
     "rssm_create", "rssm_set_weights", "rssm_unroll", "rssm_get_status",
     "rssm_last_launch_count", "rssm_destroy",
 )
@@ -77,6 +77,7 @@ def load(path: Optional[str] = None):
             "rnn_profile_entry": (I, [P, I, ctypes.POINTER(ctypes.c_char_p),
                                       ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64)]),
             "rnn_profile_reset": (I, [P]),
+            "rnn_get_trace": (I, [P, P, I, P]),
             "rssm_create": (I, [ctypes.POINTER(P), I, I, I, I]),
             "rssm_set_weights": (I, [P] + [P] * 10 + [P]),
             "rssm_unroll": (I, [P, I, I] + [P] * 8 + [P]),
@@ -193,6 +194,13 @@ def rnn_profile_entry(h, i: int):
 
 def rnn_profile_reset(h):
     _check(load().rnn_profile_reset(h))
+
+
+def rnn_get_trace(h, n_steps: int, stream=None):
+    """[n_steps, 8] int64 global-timer stamps of the first layer (see rcu.h)."""
+    out = torch.zeros((n_steps, 8), dtype=torch.int64)
+    _check(load().rnn_get_trace(h, ctypes.c_void_p(out.data_ptr()), n_steps, _stream(stream)))
+    return out
 
 
 def rnn_destroy(h):

@@ -116,6 +116,10 @@ struct rcu_rnn_s {
   int force_path = 0;
   int launches = 0;
   bool used_tc_gemm = false, used_tc_rec = false;
+  // opt-in per-step trace of the first layer's recurrent kernel
+  bool trace = false;
+  DevBuf trace_buf;
+  int trace_T = 0;
   // opt-in per-kernel timing with CUDA events on the launching stream
   bool profile = false;
   struct Pending { const char *name; cudaEvent_t a, b; };
@@ -245,6 +249,9 @@ extern "C" int rnn_set_attr(rcu_rnn_t h, int attr, int64_t value) {
     case RCU_ATTR_TEST_DROP_ARRIVAL: h->drop_arrival = value != 0; return RCU_OK;
     case RCU_ATTR_PROFILE:
       h->profile = value != 0;
+      return RCU_OK;
+    case RCU_ATTR_TRACE:
+      h->trace = value != 0;
       return RCU_OK;
     case RCU_ATTR_FORCE_PATH:
       if (value < 0 || value > 2) return fail(RCU_ERR_INVALID, "force_path must be 0, 1 or 2");
@@ -424,6 +431,11 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
 
   CU(cudaMemsetAsync(h->ctl.p, 0, std::max(cbytes, ctl_bytes(h->layers)), s));
   CU(cudaMemsetAsync(h->hx, 0, (size_t)D * 2 * B * h->Kp * es, s));
+  if (h->trace) {
+    CU(h->trace_buf.ensure((size_t)T * 8 * 8));
+    CU(cudaMemsetAsync(h->trace_buf.p, 0, (size_t)T * 8 * 8, s));
+    h->trace_T = T;
+  }
   if (h->P > 0) CU(cudaMemsetAsync(h->mx, 0, (size_t)D * B * h->Hp * es, s));
   h->begin("meta_sort", s);
   CU(launch_meta(lengths, B, T, h->meta, err, s));
@@ -504,6 +516,7 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
     p.err = err;
     p.timeout_ns = (uint64_t)h->timeout_ns;
     p.drop_arrival = h->drop_arrival && l == 0;
+    p.trace = (h->trace && l == 0) ? (unsigned long long *)h->trace_buf.p : nullptr;
     bool rec_done = false;
     const bool tc_rec = bf && h->force_path != 1 &&
                         tc_rec_supported(h->cell, H, Hout, h->P, h->nsm, B, D) &&
@@ -587,6 +600,15 @@ extern "C" int rnn_profile_entry(rcu_rnn_t h, int i, const char **name, double *
   if (name) *name = h->totals[i].first.c_str();
   if (total_ms) *total_ms = h->totals[i].second.first;
   if (count) *count = h->totals[i].second.second;
+  return RCU_OK;
+}
+
+extern "C" int rnn_get_trace(rcu_rnn_t h, int64_t *host_out, int n_steps, void *stream) {
+  if (!h || !host_out || n_steps < 0) return fail(RCU_ERR_INVALID, "rnn_get_trace: bad arguments");
+  if (!h->trace_buf.p) return fail(RCU_ERR_STATE, "rnn_get_trace: no traced forward");
+  const int n = std::min(n_steps, h->trace_T);
+  CU(cudaStreamSynchronize((cudaStream_t)stream));
+  CU(cudaMemcpy(host_out, h->trace_buf.p, (size_t)n * 8 * 8, cudaMemcpyDeviceToHost));
   return RCU_OK;
 }
 

@@ -58,13 +58,17 @@ template <> struct Op<__nv_bfloat16> {
 // `timeout_ns` on the global timer and by the shared error word: a CTA that
 // times out records DEV_TIMEOUT and every CTA then leaves its step loop.
 // Returns false when the kernel must stop.
+// Ordering: the CTA's writes precede thread 0's arrival through
+// __syncthreads, and the arrival is a release at GPU scope (cumulative), so
+// no separate full fence is needed; the waiting side reads with acquire and
+// passes the ordering on through __syncthreads.  Data exchanged this way is
+// read with L1-bypassing loads.
 __device__ __forceinline__ bool group_barrier(unsigned *ctr, unsigned target, int *err,
                                               uint64_t timeout_ns, bool skip_arrive = false) {
   __syncthreads();
   __shared__ int s_ok;
   if (threadIdx.x == 0) {
     const uint64_t deadline_ns = globaltimer_ns() + timeout_ns;
-    __threadfence();
     if (!skip_arrive) red_release_gpu_add(ctr, 1u);
     int ok = 1;
     unsigned spins = 0;
@@ -76,7 +80,6 @@ __device__ __forceinline__ bool group_barrier(unsigned *ctr, unsigned target, in
         break;
       }
     }
-    __threadfence();
     s_ok = ok && ld_volatile_int(err) == DEV_OK;
   }
   __syncthreads();

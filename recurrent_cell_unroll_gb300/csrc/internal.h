@@ -62,6 +62,7 @@ struct RecParams {
   int *err;
   uint64_t timeout_ns;
   int drop_arrival;
+  unsigned long long *trace;  // NULL, or [T][8] global-timer stamps written by CTA 0
 };
 // wbf16: weights stored bf16 (operands bf16) vs fp32.
 cudaError_t launch_recurrent_simt(const RecParams &p, bool wbf16, int nsm, cudaStream_t s);

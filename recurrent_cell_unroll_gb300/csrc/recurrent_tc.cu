@@ -35,7 +35,9 @@ constexpr int UNITS = 16;       // hidden units per CTA
 constexpr int BG = 128;         // batch rows per CTA (MMA M)
 constexpr int BK = 64;          // K per stage (128 bytes of bf16)
 constexpr int A_STAGE = BG * BK * 2;
-constexpr int NT = 192;         // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int EPI_WARPS = 16;   // 4 per TMEM lane quarter
+constexpr int UPT = UNITS / 4;  // units per epilogue thread
+constexpr int NT = 64 + 32 * EPI_WARPS;  // warp 0 TMA, warp 1 MMA, then the epilogue
 constexpr int SMEM_LIMIT = 227 * 1024;
 constexpr int MAX_STAGES = 8;
 
@@ -85,7 +87,29 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void epi_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * EPI_WARPS) : "memory");
+}
+
+// 32 lanes x 4 consecutive 32-bit TMEM columns
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
+  uint32_t r[4];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// bf16 path activations on the MUFU tanh unit (PTX tanh.approx.f32); the
+// logistic function through the identity sigmoid(x) = 1/2 + tanh(x/2)/2
+__device__ __forceinline__ float tanh_fast(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float sigmoid_fast(float x) { return fmaf(0.5f, tanh_fast(0.5f * x), 0.5f); }
 
 __device__ __forceinline__ void load16(const float *p, float (&v)[16]) {
 #pragma unroll
@@ -127,7 +151,7 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
     }
     tc::mbar_init(&ctl->wbar, 1);
     tc::mbar_init(&ctl->tfull, 1);
-    tc::mbar_init(&ctl->tfree, 4);
+    tc::mbar_init(&ctl->tfree, EPI_WARPS);
     tc::mbar_init(&ctl->mdone, 1);
     ctl->abort = 0;
     tc::fence_mbar_init();
@@ -170,6 +194,7 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
           if (!ok) { *abort = 1; break; }
         }
         fence_proxy_async_global();
+        if (p.trace && blockIdx.x == 0) p.trace[step * 8 + 0] = globaltimer_ns();
         const int arow = (d * 2 + (step & 1)) * B + row0;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!tc::mbar_wait(&ctl->empty[stage], phase ^ 1, p.err, abort, tmo)) goto producer_out;
@@ -206,6 +231,7 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
         for (int kb = 0; kb < nkb; ++kb) {
           if (!tc::mbar_wait(&ctl->full[stage], phase, p.err, abort, tmo)) { ok = false; break; }
           tc::tc_fence_after();
+          if (kb == 0 && p.trace && blockIdx.x == 0) p.trace[step * 8 + 1] = globaltimer_ns();
           const uint32_t a0 = tc::smem_u32(sA + (size_t)stage * A_STAGE);
           const uint32_t b0 = tc::smem_u32(sW + (size_t)kb * N * 128);
 #pragma unroll
@@ -217,6 +243,7 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
         }
         if (!ok) break;
         tc::mma_commit(&ctl->tfull);
+        if (p.trace && blockIdx.x == 0) p.trace[step * 8 + 2] = globaltimer_ns();
       }
       // drain: every MMA issued above completes before TMEM is released
       tc::mma_commit(&ctl->mdone);
@@ -224,142 +251,142 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
       tc::mbar_wait(&ctl->mdone, 0, nullptr, &never, 100000000ull);
     }
   } else {
-    // ---------------- epilogue: thread = batch row r (TMEM lane r)
+    // ---------------- epilogue: 16 warps; warp -> (TMEM lane quarter q, 4 units)
     const int q = warp % 4;
-    const int r = q * 32 + lane;
+    const int part = (warp - 2) / 4;           // units [part*4, part*4+4) of the CTA's 16
+    const int r = q * 32 + lane;               // batch row = TMEM lane
     const int s = row0 + r;
     const bool row_ok = s < B;
     const int ldo = p.D * p.Hout;
-    const int Kp_ = Kp;
-    __nv_bfloat16 *hx = reinterpret_cast<__nv_bfloat16 *>(p.hx) + (size_t)d * 2 * B * Kp_;
+    __nv_bfloat16 *hx = reinterpret_cast<__nv_bfloat16 *>(p.hx) + (size_t)d * 2 * B * Kp;
     const float *bhn = p.bhn[d];
-    const int nu = min(UNITS, H - u0);  // valid units of this CTA (UNITS unless H % 16)
+    const int ub = u0 + part * UPT;            // first unit of this thread
+    const int nu = max(0, min(UPT, H - ub));   // valid units of this thread
     // 16-byte vector access only where every address is 16-byte aligned
-    const bool vec_g = nu == UNITS && (H & 3) == 0;
-    const bool vec_y = nu == UNITS && (p.Hout & 3) == 0 &&
+    const bool vec_g = nu == UPT && (H & 3) == 0;
+    const bool vec_y = nu == UPT && (p.Hout & 3) == 0 &&
                        (reinterpret_cast<uintptr_t>(p.y) & 15) == 0;
-    float h[UNITS], c[UNITS], bn[UNITS];
+    float h[UPT], c[UPT], bn[UPT];
     int b = 0, len = 0;
     if (row_ok) {
       b = p.meta.sorted_idx[s];
       len = p.meta.lens_sorted[s];
     }
 #pragma unroll
-    for (int j = 0; j < UNITS; ++j) {
+    for (int j = 0; j < UPT; ++j) {
       const bool uj = row_ok && j < nu;
-      h[j] = (uj && p.h0) ? p.h0[((size_t)d * B + b) * p.Hout + u0 + j] : 0.f;
-      c[j] = (uj && p.c0 && NG == 4) ? p.c0[((size_t)d * B + b) * H + u0 + j] : 0.f;
-      bn[j] = (NG == 3 && bhn && j < nu) ? bhn[u0 + j] : 0.f;
+      h[j] = (uj && p.h0) ? p.h0[((size_t)d * B + b) * p.Hout + ub + j] : 0.f;
+      c[j] = (uj && p.c0 && NG == 4) ? p.c0[((size_t)d * B + b) * H + ub + j] : 0.f;
+      bn[j] = (NG == 3 && bhn && j < nu) ? bhn[ub + j] : 0.f;
     }
     if (row_ok) {
-      __nv_bfloat16 *dst = hx + (size_t)s * Kp_ + u0;
+      __nv_bfloat16 *dst = hx + (size_t)s * Kp + ub;
 #pragma unroll
-      for (int j = 0; j < UNITS; ++j)
+      for (int j = 0; j < UPT; ++j)
         if (j < nu) dst[j] = __float2bfloat16_rn(h[j]);
     }
     fence_proxy_async_global();
     epi_bar();
     if (threadIdx.x == 64) {
-      __threadfence();
       red_release_gpu_add(ctr, (p.drop_arrival && blockIdx.x == 0) ? 0u : 1u);
     }
     for (int step = 0; step < Tg; ++step) {
       const bool active = row_ok && step < len;
       const int tt = d == 0 ? step : len - 1 - step;
-      float gx[NG][UNITS];
+      float gx[NG][UPT];
       if (active) {
         const size_t grow = (size_t)p.meta.step_off[tt] + s;
-        const float *gp = p.G + grow * p.ldG + (size_t)d * NG * H + u0;
+        const float *gp = p.G + grow * p.ldG + (size_t)d * NG * H + ub;
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
           if (vec_g) {
-            load16(gp + (size_t)g * H, gx[g]);
+            const float4 f = __ldg(reinterpret_cast<const float4 *>(gp + (size_t)g * H));
+            gx[g][0] = f.x; gx[g][1] = f.y; gx[g][2] = f.z; gx[g][3] = f.w;
           } else {
 #pragma unroll
-            for (int j = 0; j < UNITS; ++j) gx[g][j] = j < nu ? __ldg(gp + (size_t)g * H + j) : 0.f;
+            for (int j = 0; j < UPT; ++j) gx[g][j] = j < nu ? __ldg(gp + (size_t)g * H + j) : 0.f;
           }
         }
       }
       // one thread waits for the accumulator; the verdict is shared so that
-      // all 128 epilogue threads leave the loop together
+      // all epilogue threads leave the loop together
       if (threadIdx.x == 64) ctl->go = tc::mbar_wait(&ctl->tfull, step & 1, p.err, abort, tmo);
       epi_bar();
       if (!ctl->go) break;
       tc::tc_fence_after();
-      float acc[NG][UNITS];
+      if (p.trace && blockIdx.x == 0 && threadIdx.x == 64) p.trace[step * 8 + 3] = globaltimer_ns();
+      float acc[NG][UPT];
 #pragma unroll
       for (int g = 0; g < NG; ++g)
-        tmem_ld16(tbase + (uint32_t)(g * UNITS) + ((uint32_t)(q * 32) << 16), acc[g]);
+        tmem_ld4(tbase + (uint32_t)(g * UNITS + part * UPT) + ((uint32_t)(q * 32) << 16), acc[g]);
       tc::tc_fence_before();
       if (lane == 0) tc::mbar_arrive(&ctl->tfree);
+      if (p.trace && blockIdx.x == 0 && threadIdx.x == 64) p.trace[step * 8 + 5] = globaltimer_ns();
       if (active) {
 #pragma unroll
-        for (int j = 0; j < UNITS; ++j) {
+        for (int j = 0; j < UPT; ++j) {
           if (NG == 4) {
-            const float ig = sigmoid_f(acc[0][j] + gx[0][j]);
-            const float fg = sigmoid_f(acc[1][j] + gx[1][j]);
-            const float gg = tanh_f(acc[2][j] + gx[2][j]);
-            const float og = sigmoid_f(acc[3][j] + gx[3][j]);
+            const float ig = sigmoid_fast(acc[0][j] + gx[0][j]);
+            const float fg = sigmoid_fast(acc[1][j] + gx[1][j]);
+            const float gg = tanh_fast(acc[2][j] + gx[2][j]);
+            const float og = sigmoid_fast(acc[3][j] + gx[3][j]);
             c[j] = fg * c[j] + ig * gg;
-            h[j] = og * tanh_f(c[j]);
+            h[j] = og * tanh_fast(c[j]);
           } else {
-            const float rg = sigmoid_f(gx[0][j] + acc[0][j]);
-            const float zg = sigmoid_f(gx[1][j] + acc[1][j]);
-            const float ng = tanh_f(gx[2][j] + rg * (acc[NG - 1][j] + bn[j]));
+            const float rg = sigmoid_fast(gx[0][j] + acc[0][j]);
+            const float zg = sigmoid_fast(gx[1][j] + acc[1][j]);
+            const float ng = tanh_fast(gx[2][j] + rg * (acc[NG - 1][j] + bn[j]));
             h[j] = (1.f - zg) * ng + zg * h[j];
           }
         }
-        // exchange buffer for the next step (bf16 MMA operand)
-        __nv_bfloat16 *dst = hx + (size_t)(((step & 1) ^ 1) * B + s) * Kp_ + u0;
-        if (nu == UNITS) {
-          uint4 pk[2];
-          uint32_t *w = reinterpret_cast<uint32_t *>(pk);
-#pragma unroll
-          for (int j = 0; j < UNITS / 2; ++j) {
-            __nv_bfloat162 t2 = __floats2bfloat162_rn(h[2 * j], h[2 * j + 1]);
-            w[j] = *reinterpret_cast<uint32_t *>(&t2);
-          }
-          reinterpret_cast<uint4 *>(dst)[0] = pk[0];
-          reinterpret_cast<uint4 *>(dst)[1] = pk[1];
+        // exchange buffer for the next step (bf16 MMA operand): on the critical path
+        __nv_bfloat16 *dst = hx + (size_t)(((step & 1) ^ 1) * B + s) * Kp + ub;
+        if (nu == UPT) {
+          __nv_bfloat162 lo = __floats2bfloat162_rn(h[0], h[1]);
+          __nv_bfloat162 hi = __floats2bfloat162_rn(h[2], h[3]);
+          uint2 pk;
+          pk.x = *reinterpret_cast<uint32_t *>(&lo);
+          pk.y = *reinterpret_cast<uint32_t *>(&hi);
+          *reinterpret_cast<uint2 *>(dst) = pk;
         } else {
 #pragma unroll
-          for (int j = 0; j < UNITS; ++j)
+          for (int j = 0; j < UPT; ++j)
             if (j < nu) dst[j] = __float2bfloat16_rn(h[j]);
         }
-        if (p.y) {
-          float *yo = p.y + ((size_t)tt * B + b) * ldo + (size_t)d * p.Hout + u0;
-          if (vec_y) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              reinterpret_cast<float4 *>(yo)[i] =
-                  make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
-          } else {
-#pragma unroll
-            for (int j = 0; j < UNITS; ++j)
-              if (j < nu) yo[j] = h[j];
-          }
-        }
-        if (p.ymid) {
-          __nv_bfloat16 *ym = reinterpret_cast<__nv_bfloat16 *>(p.ymid) +
-                              ((size_t)p.meta.step_off[tt] + s) * ldo + (size_t)d * p.Hout + u0;
-#pragma unroll
-          for (int j = 0; j < UNITS; ++j)
-            if (j < nu) ym[j] = __float2bfloat16_rn(h[j]);
-        }
       }
+      if (p.trace && blockIdx.x == 0 && threadIdx.x == 64) p.trace[step * 8 + 6] = globaltimer_ns();
       fence_proxy_async_global();
       epi_bar();
       if (threadIdx.x == 64) {
-        __threadfence();
-        red_release_gpu_add(ctr, 1u);
+        if (p.trace && blockIdx.x == 0) p.trace[step * 8 + 7] = globaltimer_ns();
+        red_release_gpu_add(ctr, 1u);  // release: orders the epilogue's h_t stores
+        if (p.trace && blockIdx.x == 0) p.trace[step * 8 + 4] = globaltimer_ns();
+      }
+      // outputs leave the critical path: written after h_t is published
+      if (active && p.y) {
+        float *yo = p.y + ((size_t)tt * B + b) * ldo + (size_t)d * p.Hout + ub;
+        if (vec_y) {
+          *reinterpret_cast<float4 *>(yo) = make_float4(h[0], h[1], h[2], h[3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < UPT; ++j)
+            if (j < nu) yo[j] = h[j];
+        }
+      }
+      if (active && p.ymid) {
+        __nv_bfloat16 *ym = reinterpret_cast<__nv_bfloat16 *>(p.ymid) +
+                            ((size_t)p.meta.step_off[tt] + s) * ldo + (size_t)d * p.Hout + ub;
+#pragma unroll
+        for (int j = 0; j < UPT; ++j)
+          if (j < nu) ym[j] = __float2bfloat16_rn(h[j]);
       }
     }
     if (row_ok && !*abort) {
 #pragma unroll
-      for (int j = 0; j < UNITS; ++j) {
+      for (int j = 0; j < UPT; ++j) {
         if (j >= nu) continue;
-        if (p.h_n) p.h_n[((size_t)d * B + b) * p.Hout + u0 + j] = h[j];
-        if (NG == 4 && p.c_n) p.c_n[((size_t)d * B + b) * H + u0 + j] = c[j];
+        if (p.h_n) p.h_n[((size_t)d * B + b) * p.Hout + ub + j] = h[j];
+        if (NG == 4 && p.c_n) p.c_n[((size_t)d * B + b) * H + ub + j] = c[j];
       }
     }
   }
