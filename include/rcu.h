@@ -187,6 +187,43 @@ RCU_API int rnn_get_trace(rcu_rnn_t h, int64_t *host_out, int n_steps, void *str
 RCU_API int rnn_destroy(rcu_rnn_t h);
 
 /* ------------------------------------------------------------------------ */
+/* Allocation-free single-layer LSTM                                          */
+/* ------------------------------------------------------------------------ */
+
+/* Size of the fixed device scratch behind rnn_lstm_forward_noalloc. */
+#define RCU_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * One-layer, one-direction fp32 LSTM forward that allocates no device memory
+ * and needs no handle.  It is meant for callers that must not call
+ * cudaMalloc themselves or have the library do it: code embedded in a host
+ * framework that owns the device heap, processes whose device-memory budget
+ * is fixed before they start, and loops that cannot afford an allocation
+ * (it may synchronise the device or fail under memory pressure).  The paper
+ * has no counterpart to this entry point; it computes the same LSTM as
+ * rnn_forward with cell RCU_LSTM, one layer, RCU_F32, no lengths.
+ *
+ *   x [T, B, in_dim]; W_ih [4H, in_dim]; W_hh [4H, H]; b_ih, b_hh [4H] or
+ *   NULL (zero); h0, c0 [B, H] or NULL (zero): device, fp32, PyTorch layout.
+ *   y [T, B, H]; h_n, c_n [B, H] or NULL: device outputs.
+ *
+ * Temporary memory comes from a file-scope device array of
+ * RCU_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until
+ * the process exits.  A problem whose scratch (about 16*T*B*H bytes plus
+ * 16*B*H + 16*H) exceeds that size is rejected with RCU_ERR_UNSUPPORTED before
+ * any work is enqueued.  All calls share the array and each overwrites it:
+ * calls that overlap on the GPU (e.g. on two streams) race.  The first call
+ * on a device looks up the array's device address with that device current
+ * and caches it; make that first call before any stream capture.  The call
+ * is synchronous: it returns after the work on `stream` has finished,
+ * with RCU_ERR_TIMEOUT if a device step barrier gave up.
+ */
+RCU_API int rnn_lstm_forward_noalloc(int T, int B, int in_dim, int hidden, const float *x,
+                                     const float *W_ih, const float *W_hh, const float *b_ih,
+                                     const float *b_hh, const float *h0, const float *c0,
+                                     float *y, float *h_n, float *c_n, void *stream);
+
+/* ------------------------------------------------------------------------ */
 /* RSSM prior unroll ("[Feature Request] CUDNN version of RSSM",             */
 /* pytorch/rl issue 366, Solution: RSSMPrior and unroll variant 1)           */
 /* ------------------------------------------------------------------------ */

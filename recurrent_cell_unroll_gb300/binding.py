@@ -32,7 +32,7 @@ RCU_ATTR_PROFILE, RCU_ATTR_TRACE = 4, 5
 EXPORTED = (
     "rcu_last_error", "rcu_version", "rnn_create", "rnn_set_weights", "rnn_forward",
     "rnn_get_pack", "rnn_get_status", "rnn_set_attr", "rnn_last_launch_count", "rnn_destroy",
-    "rnn_profile_entry", "rnn_profile_reset", "rnn_get_trace",
+    "rnn_profile_entry", "rnn_profile_reset", "rnn_get_trace", "rnn_lstm_forward_noalloc",
     "rssm_create", "rssm_set_weights", "rssm_unroll", "rssm_get_status",
     "rssm_last_launch_count", "rssm_destroy",
 )
@@ -78,6 +78,7 @@ def load(path: Optional[str] = None):
                                       ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64)]),
             "rnn_profile_reset": (I, [P]),
             "rnn_get_trace": (I, [P, P, I, P]),
+            "rnn_lstm_forward_noalloc": (I, [I, I, I, I] + [P] * 10 + [P]),
             "rssm_create": (I, [ctypes.POINTER(P), I, I, I, I]),
             "rssm_set_weights": (I, [P] + [P] * 10 + [P]),
             "rssm_unroll": (I, [P, I, I] + [P] * 8 + [P]),
@@ -206,6 +207,16 @@ def rnn_get_trace(h, n_steps: int, stream=None):
 def rnn_destroy(h):
     if h:
         load().rnn_destroy(h)
+
+
+def rnn_lstm_forward_noalloc(T: int, B: int, in_dim: int, hidden: int, x, W_ih, W_hh,
+                             b_ih=None, b_hh=None, h0=None, c0=None, y=None, h_n=None, c_n=None,
+                             stream=None):
+    """One-layer fp32 LSTM through the allocation-free entry point (see rcu.h)."""
+    ins = [_dev(t) for t in (x, W_ih, W_hh, b_ih, b_hh, h0, c0)]
+    outs = [_dev(t) for t in (y, h_n, c_n)]
+    _check(load().rnn_lstm_forward_noalloc(T, B, in_dim, hidden, *[k[1] for k in ins],
+                                           *[k[1] for k in outs], _stream(stream)))
 
 
 def rssm_create(state_dim: int, action_dim: int, hidden: int, rnn_hidden: int):

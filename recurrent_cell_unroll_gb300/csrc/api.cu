@@ -173,6 +173,8 @@ static size_t esize(int dtype) { return dtype == RCU_BF16 ? 2 : 4; }
 static size_t ctl_bytes(int layers) { return 64 + 16 * (size_t)layers + 64; }
 
 extern "C" const char *rcu_last_error(void) { return g_last_error.c_str(); }
+
+int rcu::set_error(int code, const char *msg) { return fail(code, "%s", msg); }
 extern "C" const char *rcu_version(void) { return "rcu 0.1 (sm_103a)"; }
 
 static void plan_simt(rcu_rnn_s *h) {

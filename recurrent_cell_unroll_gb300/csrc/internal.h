@@ -16,6 +16,9 @@ struct Meta {
   int32_t *step_off;     // [T+1] exclusive prefix of batch_sizes; step_off[T] = packed rows
 };
 
+// ---- api.cu: record `msg` as this host thread's last error; returns `code`
+int set_error(int code, const char *msg);
+
 // ---- pack.cu -------------------------------------------------------------
 // Build Meta from lengths (NULL = every row has length T).  Lengths outside
 // [1, T] raise DEV_LENGTHS in *err and are clamped so later kernels stay in bounds.
