@@ -74,6 +74,10 @@ typedef struct rcu_rssm_s *rcu_rssm_t;
 #define RCU_ATTR_FORCE_PATH 3         /* 0 = automatic, 1 = portable SIMT kernels only,
                                          2 = tensor-core (tcgen05) kernels where supported */
 #define RCU_ATTR_TRACE 5              /* 1 = record per-step timestamps (rnn_get_trace) */
+#define RCU_ATTR_TC_CLUSTER 6         /* tensor-core recurrent kernel: CTAs per thread-block
+                                         cluster that share each h tile by TMA multicast
+                                         (0 or 1 = none, 2, 4, 8; used when it divides the
+                                         number of unit groups) */
 #define RCU_ATTR_PROFILE 4            /* 1 = record a CUDA event pair around every kernel
                                          this handle launches (on the launching stream);
                                          read the totals with rnn_profile_entry */
@@ -174,12 +178,14 @@ RCU_API int rnn_profile_reset(rcu_rnn_t h);
 
 /*
  * Step trace of the first layer's recurrent kernel, recorded while
- * RCU_ATTR_TRACE is on: for each step t < n_steps, 8 global-timer stamps (ns)
- * of CTA 0 are copied to host_out[t*8 .. t*8+7] (0 where a slot is unused).
- * Tensor-core kernel slots: 0 producer saw the step barrier, 1 first h stage
- * landed, 2 last MMA issued, 3 epilogue got the accumulator, 4 epilogue
- * published h_t.  Portable kernel slots: 0 step start, 1 gates done,
- * 2 barrier passed.  Synchronises the stream.  host_out is host memory.
+ * RCU_ATTR_TRACE is on: for each step t < n_steps, 16 global-timer stamps
+ * (ns) of CTA 0 are copied to host_out[t*16 .. t*16+15] (0 where a slot is
+ * unused).  Tensor-core kernel slots: 0 producer saw the step barrier,
+ * 1 first h stage landed, 8 last h stage landed, 2 last MMA issued,
+ * 3 epilogue got the accumulator, 5 accumulator read, 6 gates done and h_t
+ * stored, 7 epilogue threads joined, 4 h_t published.  Portable kernel
+ * slots: 0 step start, 1 gates done, 2 barrier passed.  Synchronises the
+ * stream.  host_out is host memory.
  */
 RCU_API int rnn_get_trace(rcu_rnn_t h, int64_t *host_out, int n_steps, void *stream);
 

@@ -38,6 +38,13 @@ int fail(int code, const char *fmt, ...) {
                   __FILE__, __LINE__);                                                  \
   } while (0)
 
+float bf2f(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
+}
+
 // fp32 -> bf16 bits, round to nearest even (NaN kept quiet).
 uint16_t f2bf(float f) {
   uint32_t u;
@@ -90,6 +97,9 @@ struct DevBuf {
 struct LayerDirW {
   DevBuf whh, whr, bhn;  // SIMT-packed recurrent weights, projection, GRU b_hn
   DevBuf tc_whh;         // tensor-core packed recurrent weights (bf16 path)
+  // bf16 LSTMP tensor-core path: packed W_hh W_hr, fp32 copy of the rounded
+  // W_hh (initial-state term) and bf16 W_hr [P][round_up(H, 8)] (projection GEMM)
+  DevBuf fold_w, whh_f32, whr_bf;
   bool set = false;
 };
 
@@ -110,10 +120,13 @@ struct rcu_rnn_s {
   int ws_T = -1, ws_B = -1;
   int last_T = -1, last_B = -1;
   char *xp = nullptr, *g = nullptr, *ymid = nullptr, *hx = nullptr, *mx = nullptr;
+  char *mbuf = nullptr, *hx2 = nullptr;  // LSTMP tensor-core path
+  float *ytmp = nullptr;
   float *hst = nullptr, *cst = nullptr;
   int64_t timeout_ns = 2000000000LL;
   int drop_arrival = 0;
   int force_path = 0;
+  int tc_cluster = 0;  // CTAs per cluster sharing h loads in the tensor-core recurrent kernel
   int launches = 0;
   bool used_tc_gemm = false, used_tc_rec = false;
   // opt-in per-step trace of the first layer's recurrent kernel
@@ -252,6 +265,11 @@ extern "C" int rnn_set_attr(rcu_rnn_t h, int attr, int64_t value) {
     case RCU_ATTR_PROFILE:
       h->profile = value != 0;
       return RCU_OK;
+    case RCU_ATTR_TC_CLUSTER:
+      if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8)
+        return fail(RCU_ERR_INVALID, "cluster size must be 0, 1, 2, 4 or 8");
+      h->tc_cluster = (int)value;
+      return RCU_OK;
     case RCU_ATTR_TRACE:
       h->trace = value != 0;
       return RCU_OK;
@@ -353,6 +371,30 @@ extern "C" int rnn_set_weights(rcu_rnn_t h, int layer, int dir, const float *W_i
     tc_pack_whh(h->cell, H, Hout, whh.data(), packed, f2bf);
     CU(lw.tc_whh.upload(packed.data(), packed.size() * 2));
   }
+  // --- LSTMP on the tensor cores: recurrent weight W_hh W_hr over m (from the
+  //     bf16-rounded factors, product accumulated in fp32, rounded to bf16)
+  if (bf && P > 0 && tc_rec_packable(RCU_LSTM, H, H, 0)) {
+    const int G4 = nG * H, ldH = round_up(H, 8);
+    std::vector<float> whh_r((size_t)G4 * P), whr_r((size_t)P * H), wp((size_t)G4 * H, 0.f);
+    for (size_t i = 0; i < whh_r.size(); ++i) whh_r[i] = bf2f(f2bf(whh[i]));
+    for (size_t i = 0; i < whr_r.size(); ++i) whr_r[i] = bf2f(f2bf(whr[i]));
+    for (int r = 0; r < G4; ++r) {
+      float *dst = &wp[(size_t)r * H];
+      for (int q = 0; q < P; ++q) {
+        const float a = whh_r[(size_t)r * P + q];
+        const float *src = &whr_r[(size_t)q * H];
+        for (int k = 0; k < H; ++k) dst[k] += a * src[k];
+      }
+    }
+    std::vector<uint16_t> packed;
+    tc_pack_whh(RCU_LSTM, H, H, wp.data(), packed, f2bf);
+    CU(lw.fold_w.upload(packed.data(), packed.size() * 2));
+    CU(lw.whh_f32.upload(whh_r.data(), whh_r.size() * 4));
+    std::vector<uint16_t> hr((size_t)P * ldH, 0);
+    for (int q = 0; q < P; ++q)
+      for (int k = 0; k < H; ++k) hr[(size_t)q * ldH + k] = f2bf(whr[(size_t)q * H + k]);
+    CU(lw.whr_bf.upload(hr.data(), hr.size() * 2));
+  }
   lw.set = true;
   return RCU_OK;
 }
@@ -376,6 +418,13 @@ static int ensure_ws(rcu_rnn_s *h, int T, int B) {
     const size_t o_mx = take((size_t)h->D * Bm * h->Hp * es);
     const size_t o_hst = take((size_t)h->D * Bm * h->Hout * 4);
     const size_t o_cst = take((size_t)h->D * Bm * h->H * 4);
+    // LSTMP tensor-core path: m_t of every step (bf16), its exchange buffer,
+    // and the fp32 projected outputs of the non-final layers
+    const bool fold = h->P > 0 && h->dtype == RCU_BF16;
+    const size_t ldH = round_up(h->H, 8);
+    const size_t o_mbuf = fold ? take(M * h->D * h->H * 2) : 0;
+    const size_t o_hx2 = fold ? take((size_t)h->D * 2 * Bm * ldH * 2) : 0;
+    const size_t o_ytmp = (fold && h->layers > 1) ? take(M * h->D * h->P * 4) : 0;
     cudaError_t e = h->ws.ensure(off);
     if (e != cudaSuccess)
       return fail(RCU_ERR_CUDA, "workspace allocation of %zu bytes failed: %s", off,
@@ -394,6 +443,9 @@ static int ensure_ws(rcu_rnn_s *h, int T, int B) {
     h->mx = base + o_mx;
     h->hst = (float *)(base + o_hst);
     h->cst = (float *)(base + o_cst);
+    h->mbuf = fold ? base + o_mbuf : nullptr;
+    h->hx2 = fold ? base + o_hx2 : nullptr;
+    h->ytmp = (fold && h->layers > 1) ? (float *)(base + o_ytmp) : nullptr;
     h->ws_T = Tm;
     h->ws_B = Bm;
   }
@@ -434,8 +486,8 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
   CU(cudaMemsetAsync(h->ctl.p, 0, std::max(cbytes, ctl_bytes(h->layers)), s));
   CU(cudaMemsetAsync(h->hx, 0, (size_t)D * 2 * B * h->Kp * es, s));
   if (h->trace) {
-    CU(h->trace_buf.ensure((size_t)T * 8 * 8));
-    CU(cudaMemsetAsync(h->trace_buf.p, 0, (size_t)T * 8 * 8, s));
+    CU(h->trace_buf.ensure((size_t)T * 16 * 8));
+    CU(cudaMemsetAsync(h->trace_buf.p, 0, (size_t)T * 16 * 8, s));
     h->trace_T = T;
   }
   if (h->P > 0) CU(cudaMemsetAsync(h->mx, 0, (size_t)D * B * h->Hp * es, s));
@@ -519,6 +571,69 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
     p.timeout_ns = (uint64_t)h->timeout_ns;
     p.drop_arrival = h->drop_arrival && l == 0;
     p.trace = (h->trace && l == 0) ? (unsigned long long *)h->trace_buf.p : nullptr;
+
+    // ---- LSTMP on the tensor cores: recurrence on m with W_hh W_hr resident,
+    //      then the projection of every step as one GEMM
+    const int P = h->P, ldH = round_up(H, 8);
+    const bool folded = bf && P > 0 && !varlen && h->force_path != 1 && h->mbuf &&
+                        h->lw[(size_t)l * D].fold_w.p && (H % 8) == 0 && ((D * H) % 8) == 0 &&
+                        tc_rec_supported(RCU_LSTM, H, H, 0, h->nsm, B, D) &&
+                        tc_gemm_supported(H, P);
+    if (folded) {
+      if (h0) {
+        h->begin("h0_gates", s);
+        for (int d = 0; d < D; ++d)
+          CU(launch_h0_gates(G, N, (const float *)h->lw[(size_t)l * D + d].whh_f32.p,
+                             h0 + ((size_t)l * D + d) * B * P, B, T, nG * H, P, d, s));
+        h->end(s);
+      }
+      RecParams pf = p;
+      pf.Hout = H;
+      pf.Kp = ldH;
+      pf.proj = 0;
+      pf.hx = h->hx2;
+      pf.y = nullptr;
+      pf.ymid = h->mbuf;  // m_t, packed rows, bf16 [T*B][D*H]
+      pf.h0 = nullptr;    // m_{-1} does not enter: the h0 term is in G already
+      pf.h_n = nullptr;
+      CU(cudaMemsetAsync(h->hx2, 0, (size_t)D * 2 * B * ldH * 2, s));
+      TcRecParams tp;
+      tp.base = pf;
+      tp.cluster = h->tc_cluster;
+      for (int d = 0; d < D; ++d) tp.Wtc[d] = h->lw[(size_t)l * D + d].fold_w.p;
+      h->begin("recurrent_tc_lstmp", s);
+      cudaError_t e = launch_tc_recurrent(tp, h->nsm, s);
+      if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "tc recurrent: %s", cudaGetErrorString(e));
+      h->end(s);
+      h->used_tc_rec = true;
+      // projection h_t = W_hr m_t for all steps and directions
+      float *Y = last ? y : h->ytmp;
+      h->begin("projection_gemm_tc", s);
+      for (int d = 0; d < D; ++d) {
+        e = launch_tc_gemm((const __nv_bfloat16 *)h->mbuf + (size_t)d * H, D * H,
+                           (const __nv_bfloat16 *)h->lw[(size_t)l * D + d].whr_bf.p, ldH, nullptr,
+                           Y + (size_t)d * P, D * P, Mmax, nullptr, P, H, h->nsm, s, err,
+                           (uint64_t)h->timeout_ns);
+        if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "projection gemm: %s", cudaGetErrorString(e));
+      }
+      h->end(s);
+      if (h_n) {
+        h->begin("last_h", s);
+        for (int d = 0; d < D; ++d)
+          CU(launch_last_h(Y, D * P, h_n + ((size_t)l * D + d) * B * P, B, T, P, d, s));
+        h->end(s);
+      }
+      if (!last) {
+        h->begin("convert_bf16", s);
+        CU(launch_convert<__nv_bfloat16>(h->ytmp, (__nv_bfloat16 *)h->ymid, (size_t)Mmax * D * P,
+                                         s));
+        h->end(s);
+      }
+      X = h->ymid;
+      ldx = D * Hout;
+      continue;
+    }
+
     bool rec_done = false;
     const bool tc_rec = bf && h->force_path != 1 &&
                         tc_rec_supported(h->cell, H, Hout, h->P, h->nsm, B, D) &&
@@ -527,6 +642,7 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
     if (tc_rec) {
       TcRecParams tp;
       tp.base = p;
+      tp.cluster = h->tc_cluster;
       for (int d = 0; d < D; ++d) tp.Wtc[d] = h->lw[(size_t)l * D + d].tc_whh.p;
       cudaError_t e = launch_tc_recurrent(tp, h->nsm, s);
       if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "tc recurrent: %s", cudaGetErrorString(e));
@@ -610,7 +726,7 @@ extern "C" int rnn_get_trace(rcu_rnn_t h, int64_t *host_out, int n_steps, void *
   if (!h->trace_buf.p) return fail(RCU_ERR_STATE, "rnn_get_trace: no traced forward");
   const int n = std::min(n_steps, h->trace_T);
   CU(cudaStreamSynchronize((cudaStream_t)stream));
-  CU(cudaMemcpy(host_out, h->trace_buf.p, (size_t)n * 8 * 8, cudaMemcpyDeviceToHost));
+  CU(cudaMemcpy(host_out, h->trace_buf.p, (size_t)n * 16 * 8, cudaMemcpyDeviceToHost));
   return RCU_OK;
 }
 

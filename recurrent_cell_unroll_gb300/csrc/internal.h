@@ -71,6 +71,14 @@ struct RecParams {
 cudaError_t launch_recurrent_simt(const RecParams &p, bool wbf16, int nsm, cudaStream_t s);
 size_t recurrent_simt_smem(const RecParams &p, bool wbf16);
 
+// ---- lstmp_fold.cu -------------------------------------------------------------
+// G rows of each sequence's first step (direction d) += W_hh h0 (W_hh fp32 [4H][P]).
+cudaError_t launch_h0_gates(float *G, int ldG, const float *Whh, const float *h0, int B, int T,
+                            int H4, int P, int d, cudaStream_t s);
+// h_n (direction d, [B][P]) from the projected outputs Y [T*B][ldY].
+cudaError_t launch_last_h(const float *Y, int ldY, float *h_n, int B, int T, int P, int d,
+                          cudaStream_t s);
+
 // ---- rssm.cu -----------------------------------------------------------------
 struct RssmParams {
   int S, A, Hd, RH, T, B;

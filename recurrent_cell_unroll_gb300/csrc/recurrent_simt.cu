@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
   for (int step = 0; step < p.T; ++step) {
     const int nact = bsz[step];
     const bool tr = p.trace && blockIdx.x == 0 && threadIdx.x == 0;
-    if (tr) p.trace[step * 8 + 0] = globaltimer_ns();
+    if (tr) p.trace[step * 16 + 0] = globaltimer_ns();
     if (nact <= 0) break;
     const WT *hcur = hx + (size_t)(step & 1) * B * Kp;
     WT *hnxt = hx + (size_t)((step & 1) ^ 1) * B * Kp;
@@ -249,9 +249,9 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
           reinterpret_cast<WT *>(p.ymid)[row * ldo + (size_t)d * Hout + u] = Op<WT>::from_f(hv);
       }
     }
-    if (tr) p.trace[step * 8 + 1] = globaltimer_ns();
+    if (tr) p.trace[step * 16 + 1] = globaltimer_ns();
     if (!group_barrier(ctr, ++nbar * p.NU, p.err, p.timeout_ns)) return;
-    if (tr) p.trace[step * 8 + 2] = globaltimer_ns();
+    if (tr) p.trace[step * 16 + 2] = globaltimer_ns();
 
     // ---- phase 2 (LSTMP): h_t = W_hr m_t for this CTA's projection rows
     if (proj) {

@@ -143,11 +143,16 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
   unsigned *ctr = p.ctr + d * NBG + bg;
   // steps this batch group runs: the longest row of the group (rows sorted by length)
   const int Tg = row0 < B ? p.meta.lens_sorted[row0] : 0;
+  // cluster of CTAs sharing (d, bg): each issues 1/cs of the h k-blocks as
+  // multicast loads into every member; a stage is free again once all
+  // members' MMAs have consumed it
+  const uint32_t cs = tc::cluster_nctarank(), crank = tc::cluster_ctarank();
+  const uint16_t cmask = (uint16_t)((1u << cs) - 1u);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STG; ++s) {
       tc::mbar_init(&ctl->full[s], 1);
-      tc::mbar_init(&ctl->empty[s], 1);
+      tc::mbar_init(&ctl->empty[s], cs);
     }
     tc::mbar_init(&ctl->wbar, 1);
     tc::mbar_init(&ctl->tfull, 1);
@@ -159,6 +164,7 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
   if (warp == 1) tc::tmem_alloc(&ctl->tmem_base, 64);
   tc::tc_fence_before();
   __syncthreads();
+  if (cs > 1) tc::cluster_sync();  // peers' barriers exist before any multicast
   tc::tc_fence_after();
   const uint32_t tbase = ctl->tmem_base;
 
@@ -194,12 +200,18 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
           if (!ok) { *abort = 1; break; }
         }
         fence_proxy_async_global();
-        if (p.trace && blockIdx.x == 0) p.trace[step * 8 + 0] = globaltimer_ns();
+        if (p.trace && blockIdx.x == 0) p.trace[step * 16 + 0] = globaltimer_ns();
         const int arow = (d * 2 + (step & 1)) * B + row0;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!tc::mbar_wait(&ctl->empty[stage], phase ^ 1, p.err, abort, tmo)) goto producer_out;
           tc::mbar_arrive_expect_tx(&ctl->full[stage], A_STAGE);
-          tc::tma_load_2d(sA + (size_t)stage * A_STAGE, &maps.hx, &ctl->full[stage], kb * BK, arow);
+          if (cs == 1) {
+            tc::tma_load_2d(sA + (size_t)stage * A_STAGE, &maps.hx, &ctl->full[stage], kb * BK,
+                            arow);
+          } else if ((uint32_t)kb % cs == crank) {
+            tc::tma_load_2d_mc(sA + (size_t)stage * A_STAGE, &maps.hx, &ctl->full[stage],
+                               kb * BK, arow, cmask);
+          }
           pend_stage[npend % MAX_STAGES] = stage;
           pend_phase[npend % MAX_STAGES] = phase;
           ++npend;
@@ -222,28 +234,51 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = tc::idesc_bf16_f32(BG, NG * UNITS);
+      // The issuing thread is on the critical path: descriptors are built once
+      // and advanced by adding (byte offset >> 4) to the start-address field
+      // (all shared-memory offsets here stay below 256 KB, so the 14-bit
+      // field cannot carry).
+      const uint64_t adesc0 = tc::smem_desc_sw128(tc::smem_u32(sA));
+      const uint64_t bdesc0 = tc::smem_desc_sw128(tc::smem_u32(sW));
+      const uint32_t bstep = (uint32_t)(N * 128) >> 4;
+      const bool tr = p.trace && blockIdx.x == 0;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = tc::mbar_wait(&ctl->wbar, 0, p.err, abort, tmo);
       for (int step = 0; ok && step < Tg; ++step) {
         if (!tc::mbar_wait(&ctl->tfree, (step & 1) ^ 1, p.err, abort, tmo)) break;
         tc::tc_fence_after();
-        for (int kb = 0; kb < nkb; ++kb) {
+        long long cyc_wait = 0, cyc_issue = 0;
+        uint64_t bd = bdesc0;
+        for (int kb = 0; kb < nkb; ++kb, bd += bstep) {
+          const long long c0 = tr ? clock64() : 0;
           if (!tc::mbar_wait(&ctl->full[stage], phase, p.err, abort, tmo)) { ok = false; break; }
           tc::tc_fence_after();
-          if (kb == 0 && p.trace && blockIdx.x == 0) p.trace[step * 8 + 1] = globaltimer_ns();
-          const uint32_t a0 = tc::smem_u32(sA + (size_t)stage * A_STAGE);
-          const uint32_t b0 = tc::smem_u32(sW + (size_t)kb * N * 128);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            tc::mma_bf16(tbase, tc::smem_desc_sw128(a0 + kk * 32),
-                         tc::smem_desc_sw128(b0 + kk * 32), idesc, (kb | kk) != 0);
-          tc::mma_commit(&ctl->empty[stage]);
+          const long long c1 = tr ? clock64() : 0;
+          if (tr) {
+            if (kb > 0) cyc_wait += c1 - c0;
+            if (kb == 0) p.trace[step * 16 + 1] = globaltimer_ns();
+            if (kb == nkb - 1) {
+              p.trace[step * 16 + 8] = globaltimer_ns();
+              p.trace[step * 16 + 9] = cyc_wait;
+              p.trace[step * 16 + 10] = cyc_issue;
+            }
+          }
+          const uint64_t ad = adesc0 + (uint64_t)(stage * (A_STAGE >> 4));
+          tc::mma_bf16(tbase, ad, bd, idesc, kb != 0);
+          tc::mma_bf16(tbase, ad + 2, bd + 2, idesc, 1u);
+          tc::mma_bf16(tbase, ad + 4, bd + 4, idesc, 1u);
+          tc::mma_bf16(tbase, ad + 6, bd + 6, idesc, 1u);
+          if (cs == 1)
+            tc::mma_commit(&ctl->empty[stage]);
+          else
+            tc::mma_commit_mc(&ctl->empty[stage], cmask);
+          if (tr) cyc_issue += clock64() - c1;
           if (++stage == STG) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
         tc::mma_commit(&ctl->tfull);
-        if (p.trace && blockIdx.x == 0) p.trace[step * 8 + 2] = globaltimer_ns();
+        if (p.trace && blockIdx.x == 0) p.trace[step * 16 + 2] = globaltimer_ns();
       }
       // drain: every MMA issued above completes before TMEM is released
       tc::mma_commit(&ctl->mdone);
@@ -314,14 +349,14 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
       epi_bar();
       if (!ctl->go) break;
       tc::tc_fence_after();
-      if (p.trace && blockIdx.x == 0 && threadIdx.x == 64) p.trace[step * 8 + 3] = globaltimer_ns();
+      if (p.trace && blockIdx.x == 0 && threadIdx.x == 64) p.trace[step * 16 + 3] = globaltimer_ns();
       float acc[NG][UPT];
 #pragma unroll
       for (int g = 0; g < NG; ++g)
         tmem_ld4(tbase + (uint32_t)(g * UNITS + part * UPT) + ((uint32_t)(q * 32) << 16), acc[g]);
       tc::tc_fence_before();
       if (lane == 0) tc::mbar_arrive(&ctl->tfree);
-      if (p.trace && blockIdx.x == 0 && threadIdx.x == 64) p.trace[step * 8 + 5] = globaltimer_ns();
+      if (p.trace && blockIdx.x == 0 && threadIdx.x == 64) p.trace[step * 16 + 5] = globaltimer_ns();
       if (active) {
 #pragma unroll
         for (int j = 0; j < UPT; ++j) {
@@ -354,13 +389,13 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
             if (j < nu) dst[j] = __float2bfloat16_rn(h[j]);
         }
       }
-      if (p.trace && blockIdx.x == 0 && threadIdx.x == 64) p.trace[step * 8 + 6] = globaltimer_ns();
+      if (p.trace && blockIdx.x == 0 && threadIdx.x == 64) p.trace[step * 16 + 6] = globaltimer_ns();
       fence_proxy_async_global();
       epi_bar();
       if (threadIdx.x == 64) {
-        if (p.trace && blockIdx.x == 0) p.trace[step * 8 + 7] = globaltimer_ns();
+        if (p.trace && blockIdx.x == 0) p.trace[step * 16 + 7] = globaltimer_ns();
         red_release_gpu_add(ctr, 1u);  // release: orders the epilogue's h_t stores
-        if (p.trace && blockIdx.x == 0) p.trace[step * 8 + 4] = globaltimer_ns();
+        if (p.trace && blockIdx.x == 0) p.trace[step * 16 + 4] = globaltimer_ns();
       }
       // outputs leave the critical path: written after h_t is published
       if (active && p.y) {
@@ -392,6 +427,8 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
   }
   tc::tc_fence_before();
   __syncthreads();
+  // no member leaves while a peer may still deliver loads or arrivals to it
+  if (cs > 1) tc::cluster_sync();
   if (warp == 1) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tbase, 64);
@@ -477,8 +514,44 @@ cudaError_t launch_tc_recurrent(const TcRecParams &tp, int nsm, cudaStream_t s) 
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)geo.smem);
   if (e != cudaSuccess) return e;
+  const int grid = p.D * NBG * p.NU;
+  // cluster size: requested, else the largest of 4, 2 dividing the unit groups
+  // Multicast was measured not to pay on GB300 for this kernel (the MMA
+  // phase is bound by the tensor pipe's rate on these small-N MMAs, not by
+  // L2 requests), so clusters are opt-in.
+  int cs = tp.cluster > 0 ? tp.cluster : 1;
+  while (cs > 1 && (p.NU % cs) != 0) cs /= 2;
+  if (cs > 1) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) { cudaGetLastError(); cs = 1; }
+  }
   void *args[] = {&maps, &p};
-  return cudaLaunchCooperativeKernel(fn, dim3(p.D * NBG * p.NU), dim3(NT), args, geo.smem, s);
+  if (cs > 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = geo.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    int max_clusters = 0;
+    cudaLaunchConfig_t q = cfg;
+    q.numAttrs = 1;  // occupancy query on the cluster shape
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, fn, &q) == cudaSuccess &&
+        max_clusters * cs >= grid) {
+      e = cudaLaunchKernelExC(&cfg, fn, args);
+      if (e == cudaSuccess) return cudaSuccess;
+    }
+    cudaGetLastError();  // fall back to the cluster-free launch
+  }
+  return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(NT), args, geo.smem, s);
 }
 
 }  // namespace rcu

@@ -86,6 +86,10 @@ SMALL = [
                        hidden=70, h0_std=0.5, c0_std=0.5),
     wl.GRU_3L.scaled(bidir=True, layers=2, T=15, B=140, in_dim=24, hidden=40, varlen=(1, 15)),
     wl.GRU_3L.scaled(layers=1, T=9, B=256, in_dim=64, hidden=256),
+    # LSTMP on the tensor cores (recurrence on m with W_hh W_hr, projection GEMM after)
+    wl.LSTMP_2L.scaled(bidir=True, T=9, B=6, in_dim=16, hidden=64, proj=24, h0_std=0.5,
+                       c0_std=0.5),
+    wl.LSTMP_2L.scaled(layers=3, T=7, B=130, in_dim=32, hidden=128, proj=64),
 ]
 
 
@@ -219,6 +223,23 @@ def test_barrier_wait_times_out_and_context_survives():
     assert net.status() == 0
     ref = run_oracle(spec, inp)
     assert np.abs(y.cpu().numpy() - ref[0]).max() <= F32_TOL
+    net.close()
+
+
+@pytest.mark.parametrize("cluster", [2, 4])
+def test_tensor_core_multicast_clusters(cluster):
+    """h tiles shared within a thread-block cluster by TMA multicast."""
+    spec = wl.GRU_3L.scaled(layers=2, T=11, B=200, in_dim=48, hidden=128, varlen=(1, 11))
+    inp = wl.make_rnn_inputs(spec, seed=15)
+    dev = torch.device("cuda")
+    net = binding.RNN.from_spec(spec)
+    net.set_attr(binding.RCU_ATTR_TC_CLUSTER, cluster)
+    net.set_weights(inp["weights"])
+    y, hn, _ = net.forward(inp["x"].to(dev), lengths=inp["lengths"].to(dev),
+                           h0=inp["h0"].to(dev))
+    assert net.status() == 0
+    ref = run_oracle(spec, inp)
+    compare(spec, (y.cpu().numpy(), hn.cpu().numpy(), None), ref)
     net.close()
 
 
