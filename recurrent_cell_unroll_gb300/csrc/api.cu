@@ -650,16 +650,9 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
       h->used_tc_rec = true;
     }
     if (!rec_done) {
-      // shrink the batch chunk until the shared-memory plan fits
-      int CB = std::min(32, round_up(std::max(B, 1), 4));
-      for (;;) {
-        p.CB = CB;
-        const bool tiles_ok = (CB / 4) * (p.Rp / 4) <= 256 && (h->P == 0 || (CB / 4) * (p.Pcp / 4) <= 256);
-        if (tiles_ok && recurrent_simt_smem(p, bf) <= 227 * 1024) break;
-        if (CB <= 4)
-          return fail(RCU_ERR_UNSUPPORTED, "recurrent kernel: resident weights do not fit");
-        CB -= 4;
-      }
+      // the batch chunk is shrunk until the shared-memory plan fits
+      if (!plan_recurrent_simt(p, bf))
+        return fail(RCU_ERR_UNSUPPORTED, "recurrent kernel: resident weights do not fit");
       cudaError_t e = launch_recurrent_simt(p, bf, h->nsm, s);
       if (e != cudaSuccess)
         return fail(RCU_ERR_CUDA, "recurrent kernel launch: %s", cudaGetErrorString(e));

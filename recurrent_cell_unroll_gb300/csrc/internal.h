@@ -70,6 +70,8 @@ struct RecParams {
 // wbf16: weights stored bf16 (operands bf16) vs fp32.
 cudaError_t launch_recurrent_simt(const RecParams &p, bool wbf16, int nsm, cudaStream_t s);
 size_t recurrent_simt_smem(const RecParams &p, bool wbf16);
+// choose the batch chunk p.CB so that the shared-memory plan fits; false if none does
+bool plan_recurrent_simt(RecParams &p, bool wbf16);
 
 // ---- lstmp_fold.cu -------------------------------------------------------------
 // G rows of each sequence's first step (direction d) += W_hh h0 (W_hh fp32 [4H][P]).

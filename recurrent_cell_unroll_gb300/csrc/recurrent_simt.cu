@@ -9,10 +9,12 @@
 //      exchange buffer in L2,
 //   2. computes its slice of h_{t-1} W_hh^T (the "recurrent hidden-hidden
 //      dense" of "[TOPI] TE implementation of LSTM using scan",
-//      apache/tvm PR 11531) with fp32 FFMA,
-//   3. adds the precomputed input projection G, applies the gate
-//      nonlinearities and the cell update in registers, and writes h_t
-//      (exchange buffer, output) — cell state never leaves the CTA,
+//      apache/tvm PR 11531) with fp32 FFMA: 4x4 register tiles, K split over
+//      at most 8 thread groups,
+//   3. adds the input projection G (loaded for the step before the previous
+//      step's barrier, so its HBM latency is off the critical path), applies
+//      the gate nonlinearities and the cell update, and writes h_t (exchange
+//      buffer, output); h/c state stays in shared memory when it fits,
 //   4. for LSTMP, a second phase computes h_t = W_hr m_t (the
 //      "hidden-projection dense"; projection rows also resident),
 //   5. crosses the step with a bounded group barrier over the CTAs of its
@@ -30,7 +32,9 @@ namespace rcu {
 
 namespace {
 
-constexpr int NT = 256;
+constexpr int NT = 512;
+constexpr int KS_MAX = 8;
+constexpr int STATE_SMEM_MAX = 8192;  // B*U entries kept in shared memory (per array)
 
 __device__ __forceinline__ void load4(const float *p, float (&w)[4]) {
   const float4 v = *reinterpret_cast<const float4 *>(p);
@@ -62,8 +66,8 @@ struct Split {
 __host__ __device__ inline Split make_split(int CB, int Rx, int Kx) {
   Split s;
   s.tiles = (CB / 4) * (Rx / 4);
-  int ks = NT / s.tiles;
-  if (ks < 1) ks = 1;
+  int ks = s.tiles > 0 ? NT / s.tiles : 1;
+  if (ks > KS_MAX) ks = KS_MAX;
   if (ks > Kx / 4) ks = Kx / 4;
   if (ks < 1) ks = 1;
   s.ks = ks;
@@ -126,6 +130,35 @@ __device__ __forceinline__ float red_sum(const float *red, int ks, int CB, int R
   return a;
 }
 
+struct Smem {
+  size_t ws, wr, hs, red, st, total;
+};
+__host__ __device__ inline Smem smem_layout(const RecParams &p, size_t wsz) {
+  const bool proj = p.proj > 0;
+  Smem L;
+  size_t o = 0;
+  L.ws = o;
+  o += (size_t)p.Kp * p.Rp * wsz;
+  L.wr = o;
+  if (proj) o += (size_t)p.Hp * p.Pcp * wsz;
+  o = round_up_sz(o, 16);
+  L.hs = o;
+  const int Kh = p.Kp > (proj ? p.Hp : 0) ? p.Kp : p.Hp;
+  o += (size_t)Kh * p.CB * 4;
+  L.red = o;
+  const Split s1 = make_split(p.CB, p.Rp, p.Kp);
+  size_t red = (size_t)s1.ks * p.CB * p.Rp;
+  if (proj) {
+    const Split s2 = make_split(p.CB, p.Pcp, p.Hp);
+    red = red > (size_t)s2.ks * p.CB * p.Pcp ? red : (size_t)s2.ks * p.CB * p.Pcp;
+  }
+  o += red * 4;
+  L.st = o;
+  if (!proj && (size_t)p.B * p.U <= STATE_SMEM_MAX) o += (size_t)2 * p.B * p.U * 4;
+  L.total = o;
+  return L;
+}
+
 template <typename WT>
 __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -138,13 +171,12 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
   const bool proj = p.proj > 0;
   const bool prow = proj && ug < p.NP;  // owns projection rows
   const int pr0 = ug * p.Pc;
+  const Smem L = smem_layout(p, sizeof(WT));
 
-  WT *Ws = reinterpret_cast<WT *>(smem);
-  WT *Wr = Ws + (size_t)Kp * p.Rp;
-  float *hs = reinterpret_cast<float *>(
-      smem + round_up_sz(((size_t)Kp * p.Rp + (proj ? (size_t)Hp * p.Pcp : 0)) * sizeof(WT), 16));
-  const int Kh = max(Kp, proj ? Hp : 0);
-  float *red = hs + (size_t)Kh * CB;
+  WT *Ws = reinterpret_cast<WT *>(smem + L.ws);
+  WT *Wr = reinterpret_cast<WT *>(smem + L.wr);
+  float *hs = reinterpret_cast<float *>(smem + L.hs);
+  float *red = reinterpret_cast<float *>(smem + L.red);
 
   {  // resident weights
     const WT *gW = reinterpret_cast<const WT *>(p.Whh[d]) + (size_t)ug * Kp * p.Rp;
@@ -157,8 +189,29 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
   const float *bhn = p.bhn[d];
   WT *hx = reinterpret_cast<WT *>(p.hx) + (size_t)d * 2 * B * Kp;
   WT *mx = reinterpret_cast<WT *>(p.mx) + (size_t)d * B * Hp;
-  float *hst = p.hst + (size_t)d * B * Hout;
-  float *cst = p.cst + (size_t)d * B * H;
+  // h/c of the owned (row, unit) entries: shared memory [B][U] when it fits,
+  // else the global state arrays [D][B][H]
+  const bool st_smem = !proj && (size_t)B * U <= STATE_SMEM_MAX;
+  float *hS, *cS;
+  int sld, soff0;
+  if (st_smem) {
+    hS = reinterpret_cast<float *>(smem + L.st);
+    cS = hS + (size_t)B * U;
+    sld = U;
+    soff0 = 0;
+  } else {
+    hS = p.hst + (size_t)d * B * Hout;
+    cS = p.cst + (size_t)d * B * H;
+    sld = -1;  // global: index with the unit
+    soff0 = u0;
+  }
+  auto hidx = [&](int s, int j) -> size_t {
+    return sld > 0 ? (size_t)s * sld + j : (size_t)s * Hout + soff0 + j;
+  };
+  auto cidx = [&](int s, int j) -> size_t {
+    return sld > 0 ? (size_t)s * sld + j : (size_t)s * H + soff0 + j;
+  };
+  float *hst_g = p.hst + (size_t)d * B * Hout;  // projected h (LSTMP phase 2)
   const int32_t *sidx = p.meta.sorted_idx;
   const int32_t *lens = p.meta.lens_sorted;
   const int32_t *bsz = p.meta.batch_sizes;
@@ -167,13 +220,13 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
 
   // initial state of the entries this CTA owns
   for (int e = threadIdx.x; e < B * U; e += NT) {
-    const int s = e / U, u = u0 + e % U;
+    const int s = e / U, j = e % U, u = u0 + j;
     if (u >= H) continue;
     const int b = sidx[s];
-    if (lstm) cst[(size_t)s * H + u] = p.c0 ? p.c0[((size_t)d * B + b) * H + u] : 0.f;
+    if (lstm) cS[cidx(s, j)] = p.c0 ? p.c0[((size_t)d * B + b) * H + u] : 0.f;
     if (!proj) {
       const float h = p.h0 ? p.h0[((size_t)d * B + b) * Hout + u] : 0.f;
-      hst[(size_t)s * Hout + u] = h;
+      hS[hidx(s, j)] = h;
       hx[(size_t)s * Kp + u] = Op<WT>::from_f(h);
     }
   }
@@ -182,10 +235,33 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
       const int s = e / p.Pc, q = pr0 + e % p.Pc;
       if (q >= Hout) continue;
       const float h = p.h0 ? p.h0[((size_t)d * B + sidx[s]) * Hout + q] : 0.f;
-      hst[(size_t)s * Hout + q] = h;
+      hst_g[(size_t)s * Hout + q] = h;
       hx[(size_t)s * Kp + q] = Op<WT>::from_f(h);
     }
   }
+
+  // G of the next step for this thread's (row, unit) pair, loaded before the
+  // barrier that precedes the step (single-chunk steps with one pair per thread)
+  float gpre[4] = {0.f, 0.f, 0.f, 0.f};
+  bool have_pre = false;
+  auto prefetch = [&](int step) {
+    have_pre = false;
+    if (step >= p.T) return;
+    const int nn = bsz[step];
+    if (nn <= 0 || nn > CB || nn * U > NT) return;
+    const int e = threadIdx.x;
+    if (e < nn * U) {
+      const int i = e / U, j = e % U, u = u0 + j;
+      if (u < H) {
+        const int tt = d == 0 ? step : lens[i] - 1 - step;
+        const float *g = p.G + ((size_t)soff[tt] + i) * p.ldG + (size_t)d * nG * H + u;
+        for (int q = 0; q < nG; ++q) gpre[q] = __ldg(g + (size_t)q * H);
+      }
+    }
+    have_pre = true;
+  };
+
+  prefetch(0);
   unsigned nbar = 0;
   unsigned *ctr = p.ctr + d;
   const bool drop = p.drop_arrival && blockIdx.x == 0;
@@ -210,23 +286,30 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
       __syncthreads();
       chunk_matmul(Ws, p.Rp, Kp, hs, CB, red, sp1);
       __syncthreads();
+      const bool pre = have_pre && cb == 0;
       for (int e = threadIdx.x; e < nr * U; e += NT) {
         const int i = e / U, j = e % U, u = u0 + j;
         if (u >= H) continue;
         const int s = cb + i;
         const int tt = d == 0 ? step : lens[s] - 1 - step;
         const size_t row = (size_t)soff[tt] + s;
-        const float *g = p.G + row * p.ldG + (size_t)d * nG * H + u;
+        float gx[4];
+        if (pre) {
+          gx[0] = gpre[0]; gx[1] = gpre[1]; gx[2] = gpre[2]; gx[3] = gpre[3];
+        } else {
+          const float *g = p.G + row * p.ldG + (size_t)d * nG * H + u;
+          for (int q = 0; q < nG; ++q) gx[q] = __ldg(g + (size_t)q * H);
+        }
         float hv;
         if (lstm) {
-          const float ai = red_sum(red, sp1.ks, CB, p.Rp, i, 0 * U + j) + __ldg(g + 0 * H);
-          const float af = red_sum(red, sp1.ks, CB, p.Rp, i, 1 * U + j) + __ldg(g + 1 * H);
-          const float ag = red_sum(red, sp1.ks, CB, p.Rp, i, 2 * U + j) + __ldg(g + 2 * H);
-          const float ao = red_sum(red, sp1.ks, CB, p.Rp, i, 3 * U + j) + __ldg(g + 3 * H);
+          const float ai = red_sum(red, sp1.ks, CB, p.Rp, i, 0 * U + j) + gx[0];
+          const float af = red_sum(red, sp1.ks, CB, p.Rp, i, 1 * U + j) + gx[1];
+          const float ag = red_sum(red, sp1.ks, CB, p.Rp, i, 2 * U + j) + gx[2];
+          const float ao = red_sum(red, sp1.ks, CB, p.Rp, i, 3 * U + j) + gx[3];
           const float ig = sigmoid_f(ai), fg = sigmoid_f(af), gg = tanh_f(ag), og = sigmoid_f(ao);
-          float c = cst[(size_t)s * H + u];
+          float c = cS[cidx(s, j)];
           c = fg * c + ig * gg;
-          cst[(size_t)s * H + u] = c;
+          cS[cidx(s, j)] = c;
           hv = og * tanh_f(c);
           if (proj) {
             mx[(size_t)s * Hp + u] = Op<WT>::from_f(hv);
@@ -236,19 +319,20 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
           const float hr = red_sum(red, sp1.ks, CB, p.Rp, i, 0 * U + j);
           const float hz = red_sum(red, sp1.ks, CB, p.Rp, i, 1 * U + j);
           const float hn = red_sum(red, sp1.ks, CB, p.Rp, i, 2 * U + j) + (bhn ? bhn[u] : 0.f);
-          const float rg = sigmoid_f(__ldg(g + 0 * H) + hr);
-          const float zg = sigmoid_f(__ldg(g + 1 * H) + hz);
-          const float ng = tanh_f(__ldg(g + 2 * H) + rg * hn);
-          const float hprev = hst[(size_t)s * Hout + u];
+          const float rg = sigmoid_f(gx[0] + hr);
+          const float zg = sigmoid_f(gx[1] + hz);
+          const float ng = tanh_f(gx[2] + rg * hn);
+          const float hprev = hS[hidx(s, j)];
           hv = (1.f - zg) * ng + zg * hprev;
         }
-        hst[(size_t)s * Hout + u] = hv;
+        hS[hidx(s, j)] = hv;
         hnxt[(size_t)s * Kp + u] = Op<WT>::from_f(hv);
         if (p.y) p.y[((size_t)tt * B + sidx[s]) * ldo + (size_t)d * Hout + u] = hv;
         if (p.ymid)
           reinterpret_cast<WT *>(p.ymid)[row * ldo + (size_t)d * Hout + u] = Op<WT>::from_f(hv);
       }
     }
+    if (!proj) prefetch(step + 1);
     if (tr) p.trace[step * 16 + 1] = globaltimer_ns();
     if (!group_barrier(ctr, ++nbar * p.NU, p.err, p.timeout_ns)) return;
     if (tr) p.trace[step * 16 + 2] = globaltimer_ns();
@@ -270,7 +354,7 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
             const int tt = d == 0 ? step : lens[s] - 1 - step;
             const size_t row = (size_t)soff[tt] + s;
             const float hv = red_sum(red, sp2.ks, CB, p.Pcp, i, j);
-            hst[(size_t)s * Hout + q] = hv;
+            hst_g[(size_t)s * Hout + q] = hv;
             hnxt[(size_t)s * Kp + q] = Op<WT>::from_f(hv);
             if (p.y) p.y[((size_t)tt * B + sidx[s]) * ldo + (size_t)d * Hout + q] = hv;
             if (p.ymid)
@@ -279,23 +363,25 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
           }
         }
       }
+      prefetch(step + 1);
       if (!group_barrier(ctr, ++nbar * p.NU, p.err, p.timeout_ns)) return;
     }
   }
 
   // final state of each row = state after its last processed step
+  __syncthreads();
   for (int e = threadIdx.x; e < B * U; e += NT) {
-    const int s = e / U, u = u0 + e % U;
+    const int s = e / U, j = e % U, u = u0 + j;
     if (u >= H) continue;
     const int b = sidx[s];
-    if (lstm && p.c_n) p.c_n[((size_t)d * B + b) * H + u] = cst[(size_t)s * H + u];
-    if (!proj && p.h_n) p.h_n[((size_t)d * B + b) * Hout + u] = hst[(size_t)s * Hout + u];
+    if (lstm && p.c_n) p.c_n[((size_t)d * B + b) * H + u] = cS[cidx(s, j)];
+    if (!proj && p.h_n) p.h_n[((size_t)d * B + b) * Hout + u] = hS[hidx(s, j)];
   }
   if (prow && p.h_n) {
     for (int e = threadIdx.x; e < B * p.Pc; e += NT) {
       const int s = e / p.Pc, q = pr0 + e % p.Pc;
       if (q >= Hout) continue;
-      p.h_n[((size_t)d * B + sidx[s]) * Hout + q] = hst[(size_t)s * Hout + q];
+      p.h_n[((size_t)d * B + sidx[s]) * Hout + q] = hst_g[(size_t)s * Hout + q];
     }
   }
 }
@@ -303,19 +389,19 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
 }  // namespace
 
 size_t recurrent_simt_smem(const RecParams &p, bool wbf16) {
-  const size_t ws = wbf16 ? 2 : 4;
-  const bool proj = p.proj > 0;
-  size_t bytes = round_up_sz(((size_t)p.Kp * p.Rp + (proj ? (size_t)p.Hp * p.Pcp : 0)) * ws, 16);
-  const int Kh = std::max(p.Kp, proj ? p.Hp : 0);
-  bytes += (size_t)Kh * p.CB * 4;
-  const Split s1 = make_split(p.CB, p.Rp, p.Kp);
-  size_t red = (size_t)s1.ks * p.CB * p.Rp;
-  if (proj) {
-    const Split s2 = make_split(p.CB, p.Pcp, p.Hp);
-    red = std::max(red, (size_t)s2.ks * p.CB * p.Pcp);
+  return smem_layout(p, wbf16 ? 2 : 4).total;
+}
+
+bool plan_recurrent_simt(RecParams &p, bool wbf16) {
+  int CB = std::min(64, round_up(std::max(p.B, 1), 4));
+  for (;;) {
+    p.CB = CB;
+    const bool tiles_ok = (CB / 4) * (p.Rp / 4) <= NT &&
+                          (p.proj == 0 || (CB / 4) * (p.Pcp / 4) <= NT);
+    if (tiles_ok && recurrent_simt_smem(p, wbf16) <= 227 * 1024) return true;
+    if (CB <= 4) return false;
+    CB -= 4;
   }
-  bytes += red * 4;
-  return bytes;
 }
 
 cudaError_t launch_recurrent_simt(const RecParams &p, bool wbf16, int nsm, cudaStream_t s) {

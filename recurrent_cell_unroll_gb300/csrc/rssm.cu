@@ -9,12 +9,13 @@
 // which the Python loop on the page runs as ~10 launches per step.  Here one
 // launch runs all T steps.  A thread-block cluster of RC CTAs holds one copy
 // of every weight, each CTA the rows of the outputs it owns, resident in
-// shared memory (transposed, so threads read consecutive words).  Each phase
-// computes the CTA's output slice for the cluster's batch rows and
-// broadcasts it into every CTA's shared memory through distributed shared
-// memory, followed by a cluster barrier (a hardware barrier: it cannot hang
-// and needs no timeout).  Clusters take disjoint batch slices and never
-// wait on each other.
+// shared memory (transposed, [k][o]).  Each phase is a batched mat-vec over
+// the cluster's batch rows spread across all threads of the CTA as
+// (output, row, K-chunk); the chunk partials are summed from shared memory,
+// and the CTA's output slice is broadcast into every CTA's shared memory
+// through distributed shared memory, followed by a cluster barrier (a
+// hardware barrier: it cannot hang and needs no timeout).  Clusters take
+// disjoint batch slices and never wait on each other.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -27,8 +28,10 @@ namespace rcu {
 namespace {
 
 constexpr int RC = 8;    // CTAs per cluster
-constexpr int NT = 256;
-constexpr int MAXBC = 8; // batch rows per cluster (register accumulators)
+constexpr int NT = 512;
+constexpr int MAXBC = 8; // batch rows per cluster
+constexpr int KS_MAX = 8;
+constexpr size_t PRELOAD_MAX = 32 * 1024;  // bytes of actions+eps kept in shared memory
 
 struct Dims {
   int S, A, Hd, RH, Ha, Ua, Sa, Bc;
@@ -44,12 +47,23 @@ __host__ __device__ inline Dims make_dims(int S, int A, int Hd, int RH, int Bc) 
   return d;
 }
 
+__host__ __device__ inline int split_of(int O, int nr, int K) {
+  int ks = NT / (O * nr > 0 ? O * nr : 1);
+  if (ks > KS_MAX) ks = KS_MAX;
+  if (ks > K) ks = K;
+  return ks < 1 ? 1 : ks;
+}
+
 // shared-memory carve-up (floats)
 struct Layout {
-  size_t w1, b1, wih, whh, bih, bhh, w2, b2, w3, b3;   // weights (transposed [k][o])
-  size_t st, av, bel, qv, total;                        // vectors
+  size_t w1, b1, wih, whh, bih, bhh, w2, b2, w3, b3;  // weights (transposed [k][o])
+  size_t st, av, bel, qv;                              // vectors, [Bc][width]
+  size_t part1, part2;                                 // chunk partials
+  size_t act, eps;                                     // preloaded actions / noise
+  size_t total;
+  bool preload;
 };
-__host__ __device__ inline Layout make_layout(const Dims &d) {
+__host__ __device__ inline Layout make_layout(const Dims &d, int T) {
   Layout L;
   size_t o = 0;
   auto take = [&](size_t n) { size_t r = o; o += (n + 3) & ~size_t(3); return r; };
@@ -67,6 +81,14 @@ __host__ __device__ inline Layout make_layout(const Dims &d) {
   L.av = take((size_t)d.Bc * d.Hd);
   L.bel = take((size_t)2 * d.Bc * d.RH);
   L.qv = take((size_t)d.Bc * d.Hd);
+  L.part1 = take((size_t)KS_MAX * d.Bc * 3 * d.Ua > (size_t)KS_MAX * d.Bc * d.Ha
+                     ? (size_t)KS_MAX * d.Bc * 3 * d.Ua
+                     : (size_t)KS_MAX * d.Bc * (d.Ha > 2 * d.Sa ? d.Ha : 2 * d.Sa));
+  L.part2 = take((size_t)KS_MAX * d.Bc * 3 * d.Ua);
+  const size_t pre = (size_t)T * d.Bc * (d.A + d.S);
+  L.preload = pre * 4 <= PRELOAD_MAX;
+  L.act = take(L.preload ? (size_t)T * d.Bc * d.A : 0);
+  L.eps = take(L.preload ? (size_t)T * d.Bc * d.S : 0);
   L.total = o;
   return L;
 }
@@ -76,22 +98,33 @@ __device__ __forceinline__ float softplus_f(float v) {
   return fmaxf(v, 0.f) + log1pf(expf(-fabsf(v)));
 }
 
-// out[r][o] = sum_k Wt[k*O + o] * v[r*ldv + k] for o < O, r < nr; every
-// thread takes one output column and all rows (nr <= MAXBC accumulators);
-// columns beyond the block size loop.
-template <int NR>
-__device__ __forceinline__ void matvec_rows(const float *Wt, int O, int K, const float *v, int ldv,
-                                            int o, float (&acc)[MAXBC]) {
-#pragma unroll
-  for (int r = 0; r < MAXBC; ++r) acc[r] = 0.f;
-  for (int k = 0; k < K; ++k) {
-    const float w = Wt[(size_t)k * O + o];
-#pragma unroll
-    for (int r = 0; r < NR; ++r) acc[r] = fmaf(w, v[r * ldv + k], acc[r]);
+// part[q][r][o] = sum over K-chunk q of Wt[k*O + o] * V[r*ldv + k], for
+// o < O, r < nr, q < ks; thread t = (o, r, q) with o fastest.
+__device__ __forceinline__ void matvec_part(const float *Wt, int O, int K, const float *V,
+                                            int ldv, int nr, int ks, float *part) {
+  const int n = O * nr * ks;
+  const int kc = ceil_div(K, ks);
+  for (int t = threadIdx.x; t < n; t += NT) {
+    const int o = t % O, r = (t / O) % nr, q = t / (O * nr);
+    const int k0 = q * kc, k1 = min(K, k0 + kc);
+    const float *v = V + (size_t)r * ldv;
+    float a0 = 0.f, a1 = 0.f;
+    int k = k0;
+    for (; k + 1 < k1; k += 2) {
+      a0 = fmaf(Wt[(size_t)k * O + o], v[k], a0);
+      a1 = fmaf(Wt[(size_t)(k + 1) * O + o], v[k + 1], a1);
+    }
+    if (k < k1) a0 = fmaf(Wt[(size_t)k * O + o], v[k], a0);
+    part[((size_t)q * nr + r) * O + o] = a0 + a1;
   }
 }
 
-template <int NR>
+__device__ __forceinline__ float part_sum(const float *part, int O, int nr, int ks, int r, int o) {
+  float a = 0.f;
+  for (int q = 0; q < ks; ++q) a += part[((size_t)q * nr + r) * O + o];
+  return a;
+}
+
 __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
     rssm_kernel(const RssmParams p, int Bc) {
   extern __shared__ __align__(16) float sm[];
@@ -101,14 +134,14 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
   const int b0 = q * Bc;
   const int nr = min(Bc, p.B - b0);  // rows of this cluster (uniform across the cluster)
   const Dims d = make_dims(p.S, p.A, p.Hd, p.RH, Bc);
-  const Layout L = make_layout(d);
+  const Layout L = make_layout(d, p.T);
   const int S = d.S, A = d.A, Hd = d.Hd, RH = d.RH, SA = S + A;
   const int i0 = c * d.Ha, ni = max(0, min(d.Ha, Hd - i0));   // owned a / q outputs
   const int j0 = c * d.Ua, nj = max(0, min(d.Ua, RH - j0));   // owned GRU units
   const int s0 = c * d.Sa, ns = max(0, min(d.Sa, S - s0));    // owned state entries
   const int tid = threadIdx.x;
 
-  // ---- resident weights, transposed to [k][o]
+  // ---- resident weights, transposed to [k][o]; rows of outputs not owned are zero
   for (int e = tid; e < SA * d.Ha; e += NT) {
     const int k = e / d.Ha, o = e % d.Ha;
     sm[L.w1 + e] = o < ni ? p.W1[(size_t)(i0 + o) * SA + k] : 0.f;
@@ -152,95 +185,109 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
     sm[L.bel + e] = (r < nr && p.belief0) ? p.belief0[(size_t)(b0 + r) * RH + k] : 0.f;
   }
   for (int e = tid; e < Bc * Hd; e += NT) { sm[L.av + e] = 0.f; sm[L.qv + e] = 0.f; }
+  if (L.preload) {
+    for (int e = tid; e < p.T * Bc * A; e += NT) {
+      const int t = e / (Bc * A), r = (e / A) % Bc, k = e % A;
+      sm[L.act + e] = r < nr ? p.actions[((size_t)t * p.B + b0 + r) * A + k] : 0.f;
+    }
+    for (int e = tid; e < p.T * Bc * S; e += NT) {
+      const int t = e / (Bc * S), r = (e / S) % Bc, k = e % S;
+      sm[L.eps + e] = r < nr ? p.eps[((size_t)t * p.B + b0 + r) * S + k] : 0.f;
+    }
+  }
   cluster.sync();
 
   float *rem[RC];
 #pragma unroll
   for (int r = 0; r < RC; ++r) rem[r] = cluster.map_shared_rank(sm, r);
 
-  float acc[MAXBC], acc2[MAXBC];
+  const int ks1 = split_of(d.Ha, Bc, SA);
+  const int ks2a = split_of(3 * d.Ua, Bc, Hd), ks2b = split_of(3 * d.Ua, Bc, RH);
+  const int ks3 = split_of(d.Ha, Bc, RH);
+  const int ks4 = split_of(2 * d.Sa, Bc, Hd);
+  float *part1 = sm + L.part1, *part2 = sm + L.part2;
+
   for (int t = 0; t < p.T; ++t) {
     const int cur = t & 1;
     float *bel_cur = sm + L.bel + (size_t)cur * Bc * RH;
     const size_t bel_nxt = L.bel + (size_t)(cur ^ 1) * Bc * RH;
-    // ---- phase 1: a = ELU(W1 [state, action] + b1), owned outputs
-    if (tid < ni) {
-      const int o = tid;
-      matvec_rows<NR>(sm + L.w1, d.Ha, S, sm + L.st, S, o, acc);
-      for (int k = 0; k < A; ++k) {
-        const float w = sm[L.w1 + (size_t)(S + k) * d.Ha + o];
-#pragma unroll
-        for (int r = 0; r < NR; ++r)
-          if (r < nr) acc[r] = fmaf(w, __ldg(p.actions + ((size_t)t * p.B + b0 + r) * A + k), acc[r]);
+    // ---- phase 1: a = ELU(W1 [state, action] + b1), owned outputs.
+    // The input [state | action] of row r is read as two segments.
+    {
+      const int O = d.Ha, n = O * Bc * ks1, kc = ceil_div(SA, ks1);
+      for (int e = tid; e < n; e += NT) {
+        const int o = e % O, r = (e / O) % Bc, qq = e / (O * Bc);
+        const int k0 = qq * kc, k1 = min(SA, k0 + kc);
+        float a = 0.f;
+        for (int k = k0; k < k1; ++k) {
+          float v;
+          if (k < S) v = sm[L.st + (size_t)r * S + k];
+          else if (L.preload) v = sm[L.act + ((size_t)t * Bc + r) * A + (k - S)];
+          else v = r < nr ? __ldg(p.actions + ((size_t)t * p.B + b0 + r) * A + (k - S)) : 0.f;
+          a = fmaf(sm[L.w1 + (size_t)k * O + o], v, a);
+        }
+        part1[((size_t)qq * Bc + r) * O + o] = a;
       }
-      const float bb = sm[L.b1 + o];
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        const float a = elu_f(acc[r] + bb);
+      __syncthreads();
+      for (int e = tid; e < ni * Bc; e += NT) {
+        const int o = e % ni, r = e / ni;
+        const float a = elu_f(part_sum(part1, O, Bc, ks1, r, o) + sm[L.b1 + o]);
 #pragma unroll
         for (int x = 0; x < RC; ++x) rem[x][L.av + (size_t)r * Hd + i0 + o] = a;
       }
     }
     cluster.sync();
     // ---- phase 2: GRUCell(a, belief) for owned units
-    if (tid < nj) {
-      const int j = tid;
-      float gi[3][MAXBC], gh[3][MAXBC];
+    matvec_part(sm + L.wih, 3 * d.Ua, Hd, sm + L.av, Hd, Bc, ks2a, part1);
+    matvec_part(sm + L.whh, 3 * d.Ua, RH, bel_cur, RH, Bc, ks2b, part2);
+    __syncthreads();
+    for (int e = tid; e < nj * Bc; e += NT) {
+      const int j = e % nj, r = e / nj;
+      const int O = 3 * d.Ua;
+      float gi[3], gh[3];
 #pragma unroll
       for (int g = 0; g < 3; ++g) {
-        matvec_rows<NR>(sm + L.wih, 3 * d.Ua, Hd, sm + L.av, Hd, g * d.Ua + j, acc);
-        matvec_rows<NR>(sm + L.whh, 3 * d.Ua, RH, bel_cur, RH, g * d.Ua + j, acc2);
-#pragma unroll
-        for (int r = 0; r < MAXBC; ++r) {
-          gi[g][r] = acc[r] + sm[L.bih + g * d.Ua + j];
-          gh[g][r] = acc2[r] + sm[L.bhh + g * d.Ua + j];
-        }
+        gi[g] = part_sum(part1, O, Bc, ks2a, r, g * d.Ua + j) + sm[L.bih + g * d.Ua + j];
+        gh[g] = part_sum(part2, O, Bc, ks2b, r, g * d.Ua + j) + sm[L.bhh + g * d.Ua + j];
       }
+      const float rg = sigmoid_f(gi[0] + gh[0]);
+      const float zg = sigmoid_f(gi[1] + gh[1]);
+      const float ng = tanh_f(gi[2] + rg * gh[2]);
+      const float hb = (1.f - zg) * ng + zg * bel_cur[(size_t)r * RH + j0 + j];
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        const float rg = sigmoid_f(gi[0][r] + gh[0][r]);
-        const float zg = sigmoid_f(gi[1][r] + gh[1][r]);
-        const float ng = tanh_f(gi[2][r] + rg * gh[2][r]);
-        const float hb = (1.f - zg) * ng + zg * bel_cur[r * RH + j0 + j];
-#pragma unroll
-        for (int x = 0; x < RC; ++x) rem[x][bel_nxt + (size_t)r * RH + j0 + j] = hb;
-        if (r < nr) p.beliefs[((size_t)t * p.B + b0 + r) * RH + j0 + j] = hb;
-      }
+      for (int x = 0; x < RC; ++x) rem[x][bel_nxt + (size_t)r * RH + j0 + j] = hb;
+      if (r < nr) p.beliefs[((size_t)t * p.B + b0 + r) * RH + j0 + j] = hb;
     }
     cluster.sync();
     // ---- phase 3: q = ELU(W2 belief + b2), owned outputs
-    if (tid < ni) {
-      const int o = tid;
-      matvec_rows<NR>(sm + L.w2, d.Ha, RH, sm + bel_nxt, RH, o, acc);
-      const float bb = sm[L.b2 + o];
+    matvec_part(sm + L.w2, d.Ha, RH, sm + bel_nxt, RH, Bc, ks3, part1);
+    __syncthreads();
+    for (int e = tid; e < ni * Bc; e += NT) {
+      const int o = e % ni, r = e / ni;
+      const float qv = elu_f(part_sum(part1, d.Ha, Bc, ks3, r, o) + sm[L.b2 + o]);
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        const float qv = elu_f(acc[r] + bb);
-#pragma unroll
-        for (int x = 0; x < RC; ++x) rem[x][L.qv + (size_t)r * Hd + i0 + o] = qv;
-      }
+      for (int x = 0; x < RC; ++x) rem[x][L.qv + (size_t)r * Hd + i0 + o] = qv;
     }
     cluster.sync();
     // ---- phase 4: p = W3 q + b3 -> mean, std, sampled state (owned entries)
-    if (tid < ns) {
-      const int j = tid;
-      matvec_rows<NR>(sm + L.w3, 2 * d.Sa, Hd, sm + L.qv, Hd, j, acc);
-      matvec_rows<NR>(sm + L.w3, 2 * d.Sa, Hd, sm + L.qv, Hd, d.Sa + j, acc2);
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        const float mean = acc[r] + sm[L.b3 + j];
-        const float sd = softplus_f(acc2[r] + sm[L.b3 + d.Sa + j]) + 0.1f;
-        float st = mean;
-        if (r < nr) {
-          const size_t o = ((size_t)t * p.B + b0 + r) * S + s0 + j;
-          st = fmaf(__ldg(p.eps + o), sd, mean);
-          p.means[o] = mean;
-          p.stds[o] = sd;
-          p.states[o] = st;
-        }
-#pragma unroll
-        for (int x = 0; x < RC; ++x) rem[x][L.st + (size_t)r * S + s0 + j] = st;
+    matvec_part(sm + L.w3, 2 * d.Sa, Hd, sm + L.qv, Hd, Bc, ks4, part1);
+    __syncthreads();
+    for (int e = tid; e < ns * Bc; e += NT) {
+      const int j = e % ns, r = e / ns;
+      const float mean = part_sum(part1, 2 * d.Sa, Bc, ks4, r, j) + sm[L.b3 + j];
+      const float sd =
+          softplus_f(part_sum(part1, 2 * d.Sa, Bc, ks4, r, d.Sa + j) + sm[L.b3 + d.Sa + j]) + 0.1f;
+      float st = mean;
+      if (r < nr) {
+        const size_t o = ((size_t)t * p.B + b0 + r) * S + s0 + j;
+        const float ev = L.preload ? sm[L.eps + ((size_t)t * Bc + r) * S + s0 + j] : __ldg(p.eps + o);
+        st = fmaf(ev, sd, mean);
+        p.means[o] = mean;
+        p.stds[o] = sd;
+        p.states[o] = st;
       }
+#pragma unroll
+      for (int x = 0; x < RC; ++x) rem[x][L.st + (size_t)r * S + s0 + j] = st;
     }
     cluster.sync();
   }
@@ -255,44 +302,29 @@ int pick_bc(int B, int nsm) {
   return bc;
 }
 
-size_t smem_bytes(int S, int A, int Hd, int RH, int Bc) {
-  return make_layout(make_dims(S, A, Hd, RH, Bc)).total * sizeof(float);
-}
-
-template <int NR>
-cudaError_t launch_nr(const RssmParams &p, int Bc, int grid, size_t smem, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute((const void *)rssm_kernel<NR>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  rssm_kernel<NR><<<grid, NT, smem, s>>>(p, Bc);
-  return cudaGetLastError();
+size_t smem_bytes(int S, int A, int Hd, int RH, int Bc, int T) {
+  return make_layout(make_dims(S, A, Hd, RH, Bc), T).total * sizeof(float);
 }
 
 }  // namespace
 
 bool rssm_supported(int S, int A, int Hd, int RH) {
   if (S < 1 || A < 0 || Hd < 1 || RH < 1) return false;
-  if (ceil_div(Hd, RC) > NT || ceil_div(RH, RC) > NT || ceil_div(S, RC) > NT) return false;
-  return smem_bytes(S, A, Hd, RH, 1) <= 227 * 1024;
+  return smem_bytes(S, A, Hd, RH, 1, 0) <= 227 * 1024;
 }
 
 cudaError_t launch_rssm(const RssmParams &p, int nsm, cudaStream_t s, int *clusters_used) {
   int Bc = pick_bc(p.B, nsm);
-  while (Bc > 1 && smem_bytes(p.S, p.A, p.Hd, p.RH, Bc) > 227 * 1024) --Bc;
-  const size_t smem = smem_bytes(p.S, p.A, p.Hd, p.RH, Bc);
+  while (Bc > 1 && smem_bytes(p.S, p.A, p.Hd, p.RH, Bc, p.T) > 227 * 1024) --Bc;
+  const size_t smem = smem_bytes(p.S, p.A, p.Hd, p.RH, Bc, p.T);
+  if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
   const int clusters = ceil_div(p.B, Bc);
   if (clusters_used) *clusters_used = clusters;
-  const int grid = clusters * RC;
-  switch (Bc) {
-    case 1: return launch_nr<1>(p, Bc, grid, smem, s);
-    case 2: return launch_nr<2>(p, Bc, grid, smem, s);
-    case 3: return launch_nr<3>(p, Bc, grid, smem, s);
-    case 4: return launch_nr<4>(p, Bc, grid, smem, s);
-    case 5: return launch_nr<5>(p, Bc, grid, smem, s);
-    case 6: return launch_nr<6>(p, Bc, grid, smem, s);
-    case 7: return launch_nr<7>(p, Bc, grid, smem, s);
-    default: return launch_nr<8>(p, Bc, grid, smem, s);
-  }
+  cudaError_t e = cudaFuncSetAttribute((const void *)rssm_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  rssm_kernel<<<clusters * RC, NT, smem, s>>>(p, Bc);
+  return cudaGetLastError();
 }
 
 }  // namespace rcu
