@@ -269,6 +269,18 @@ RCU_API int rssm_unroll(rcu_rssm_t h, int T, int B, const float *state0, const f
                 float *beliefs, void *stream);
 
 RCU_API int rssm_get_status(rcu_rssm_t h, void *stream);
+
+/* Attributes of an RSSM handle: RCU_ATTR_TRACE (1 = record per-step stamps). */
+RCU_API int rssm_set_attr(rcu_rssm_t h, int attr, int64_t value);
+
+/*
+ * Step trace of the last traced rssm_unroll: for each step t < n_steps, 16
+ * stamps of CTA 0 copied to host_out[t*16 ..]: global timer (ns) at slots
+ * 0 step start, 1 phase 1 done, 2 phase 2 done, 3 phase 3 done, 4 phase 4
+ * done; SM clock cycles at 8 phase-2 mat-vec done, 9 phase-2 gates done,
+ * 10 phase-1 partials done.  Synchronises the stream; host_out is host memory.
+ */
+RCU_API int rssm_get_trace(rcu_rssm_t h, int64_t *host_out, int n_steps, void *stream);
 RCU_API int rssm_last_launch_count(rcu_rssm_t h);
 RCU_API int rssm_destroy(rcu_rssm_t h);
 

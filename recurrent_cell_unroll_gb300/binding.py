@@ -34,7 +34,7 @@ EXPORTED = (
     "rnn_get_pack", "rnn_get_status", "rnn_set_attr", "rnn_last_launch_count", "rnn_destroy",
     "rnn_profile_entry", "rnn_profile_reset", "rnn_get_trace", "rnn_lstm_forward_noalloc",
     "rssm_create", "rssm_set_weights", "rssm_unroll", "rssm_get_status",
-    "rssm_last_launch_count", "rssm_destroy",
+    "rssm_last_launch_count", "rssm_destroy", "rssm_set_attr", "rssm_get_trace",
 )
 
 _lib = None
@@ -85,6 +85,8 @@ def load(path: Optional[str] = None):
             "rssm_get_status": (I, [P, P]),
             "rssm_last_launch_count": (I, [P]),
             "rssm_destroy": (I, [P]),
+            "rssm_set_attr": (I, [P, I, I64]),
+            "rssm_get_trace": (I, [P, P, I, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -244,6 +246,17 @@ def rssm_get_status(h, stream=None) -> int:
 
 def rssm_last_launch_count(h) -> int:
     return load().rssm_last_launch_count(h)
+
+
+def rssm_set_attr(h, attr: int, value: int):
+    _check(load().rssm_set_attr(h, attr, value))
+
+
+def rssm_get_trace(h, n_steps: int, stream=None):
+    """[n_steps, 16] int64 stamps of the last traced rssm_unroll (see rcu.h)."""
+    out = torch.zeros((n_steps, 16), dtype=torch.int64)
+    _check(load().rssm_get_trace(h, ctypes.c_void_p(out.data_ptr()), n_steps, _stream(stream)))
+    return out
 
 
 def rssm_destroy(h):

@@ -747,7 +747,26 @@ struct rcu_rssm_s {
   bool set = false;
   int launches = 0;
   DevBuf ctl;
+  bool trace = false;
+  DevBuf trace_buf;
+  int trace_T = 0;
 };
+
+extern "C" int rssm_set_attr(rcu_rssm_t h, int attr, int64_t value) {
+  if (!h) return fail(RCU_ERR_INVALID, "rssm_set_attr: NULL handle");
+  if (attr != RCU_ATTR_TRACE) return fail(RCU_ERR_INVALID, "rssm_set_attr: unknown attribute %d", attr);
+  h->trace = value != 0;
+  return RCU_OK;
+}
+
+extern "C" int rssm_get_trace(rcu_rssm_t h, int64_t *host_out, int n_steps, void *stream) {
+  if (!h || !host_out || n_steps < 0) return fail(RCU_ERR_INVALID, "rssm_get_trace: bad arguments");
+  if (!h->trace_buf.p) return fail(RCU_ERR_STATE, "rssm_get_trace: no traced unroll");
+  const int n = std::min(n_steps, h->trace_T);
+  CU(cudaStreamSynchronize((cudaStream_t)stream));
+  CU(cudaMemcpy(host_out, h->trace_buf.p, (size_t)n * 16 * 8, cudaMemcpyDeviceToHost));
+  return RCU_OK;
+}
 
 extern "C" int rssm_create(rcu_rssm_t *out, int state_dim, int action_dim, int hidden,
                            int rnn_hidden) {
@@ -812,6 +831,13 @@ extern "C" int rssm_unroll(rcu_rssm_t h, int T, int B, const float *state0, cons
   p.W3 = (const float *)h->W3.p; p.b3 = (const float *)h->b3.p;
   p.state0 = state0; p.belief0 = belief0; p.actions = actions; p.eps = eps;
   p.means = means; p.stds = stds; p.states = states; p.beliefs = beliefs;
+  p.trace = nullptr;
+  if (h->trace) {
+    CU(h->trace_buf.ensure((size_t)T * 16 * 8));
+    CU(cudaMemsetAsync(h->trace_buf.p, 0, (size_t)T * 16 * 8, (cudaStream_t)stream));
+    h->trace_T = T;
+    p.trace = (unsigned long long *)h->trace_buf.p;
+  }
   int clusters = 0;
   cudaError_t e = launch_rssm(p, h->nsm, (cudaStream_t)stream, &clusters);
   if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rssm kernel launch: %s", cudaGetErrorString(e));

@@ -63,6 +63,34 @@ template <> struct Op<__nv_bfloat16> {
 // no separate full fence is needed; the waiting side reads with acquire and
 // passes the ordering on through __syncthreads.  Data exchanged this way is
 // read with L1-bypassing loads.
+// Split form of group_barrier: group_arrive publishes the CTA's writes made
+// so far; work placed between the two calls (output stores, loads of the
+// next step's inputs) is not waited for by this arrival's release.
+__device__ __forceinline__ void group_arrive(unsigned *ctr, bool skip_arrive = false) {
+  __syncthreads();
+  if (threadIdx.x == 0 && !skip_arrive) red_release_gpu_add(ctr, 1u);
+}
+__device__ __forceinline__ bool group_wait(unsigned *ctr, unsigned target, int *err,
+                                           uint64_t timeout_ns) {
+  __shared__ int s_ok2;
+  if (threadIdx.x == 0) {
+    const uint64_t deadline_ns = globaltimer_ns() + timeout_ns;
+    int ok = 1;
+    unsigned spins = 0;
+    while (ld_acquire_gpu(ctr) < target) {
+      if (ld_volatile_int(err) != DEV_OK) { ok = 0; break; }
+      if ((++spins & 63u) == 0 && globaltimer_ns() > deadline_ns) {
+        atomicCAS(err, DEV_OK, DEV_TIMEOUT);
+        ok = 0;
+        break;
+      }
+    }
+    s_ok2 = ok && ld_volatile_int(err) == DEV_OK;
+  }
+  __syncthreads();
+  return s_ok2 != 0;
+}
+
 __device__ __forceinline__ bool group_barrier(unsigned *ctr, unsigned target, int *err,
                                               uint64_t timeout_ns, bool skip_arrive = false) {
   __syncthreads();

@@ -87,6 +87,7 @@ struct RssmParams {
   const float *W1, *b1, *Wih, *Whh, *bih, *bhh, *W2, *b2, *W3, *b3; // PyTorch layout, fp32
   const float *state0, *belief0, *actions, *eps;
   float *means, *stds, *states, *beliefs;
+  unsigned long long *trace;  // NULL, or [T][16] stamps written by CTA 0 (see rssm_get_trace)
 };
 cudaError_t launch_rssm(const RssmParams &p, int nsm, cudaStream_t s, int *clusters_used);
 bool rssm_supported(int S, int A, int Hd, int RH);

@@ -110,17 +110,31 @@ __device__ __forceinline__ void chunk_matmul(const WT *Wsm, int Rx, int Kx, cons
   }
 }
 
-// hs[k][i] = src[(row0 + i) * ld + k] for i < nr (0 for i >= nr), k < Kx
+// hs[k][i] = src[(row0 + i) * ld + k] for i < nr (0 for i >= nr), k < Kx.
+// Loads are issued LB at a time into registers before any store, so their L2
+// latencies overlap.
 template <typename WT>
 __device__ __forceinline__ void load_chunk_T(const WT *src, int ld, int row0, int nr, int Kx,
                                              int CB, float *hs) {
-  const int nq = Kx / 4;
-  for (int e = threadIdx.x; e < CB * nq; e += NT) {
-    const int i = e % CB, k = (e / CB) * 4;
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
-    if (i < nr) ldcg4(src + (size_t)(row0 + i) * ld + k, v);
+  constexpr int LB = 8;
+  const int n = CB * (Kx / 4);
+  for (int base = threadIdx.x; base < n; base += NT * LB) {
+    float v[LB][4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) hs[(size_t)(k + q) * CB + i] = v[q];
+    for (int u = 0; u < LB; ++u) {
+      const int e = base + u * NT;
+      const int i = e % CB, k = (e / CB) * 4;
+      v[u][0] = v[u][1] = v[u][2] = v[u][3] = 0.f;
+      if (e < n && i < nr) ldcg4(src + (size_t)(row0 + i) * ld + k, v[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < LB; ++u) {
+      const int e = base + u * NT;
+      if (e >= n) break;
+      const int i = e % CB, k = (e / CB) * 4;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) hs[(size_t)(k + q) * CB + i] = v[u][q];
+    }
   }
 }
 
@@ -277,6 +291,10 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
     if (nact <= 0) break;
     const WT *hcur = hx + (size_t)(step & 1) * B * Kp;
     WT *hnxt = hx + (size_t)((step & 1) ^ 1) * B * Kp;
+    // one (row, unit) pair per thread: its output store is deferred (non-LSTMP)
+    const bool one = !proj && nact <= CB && nact * U <= NT;
+    float yv = 0.f;
+    size_t y_at = SIZE_MAX, ym_at = SIZE_MAX;
 
     // ---- phase 1: gates and cell update for this CTA's units
     for (int cb = 0; cb < nact; cb += CB) {
@@ -327,14 +345,28 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
         }
         hS[hidx(s, j)] = hv;
         hnxt[(size_t)s * Kp + u] = Op<WT>::from_f(hv);
-        if (p.y) p.y[((size_t)tt * B + sidx[s]) * ldo + (size_t)d * Hout + u] = hv;
-        if (p.ymid)
-          reinterpret_cast<WT *>(p.ymid)[row * ldo + (size_t)d * Hout + u] = Op<WT>::from_f(hv);
+        const size_t yo = ((size_t)tt * B + sidx[s]) * ldo + (size_t)d * Hout + u;
+        const size_t ymo = row * ldo + (size_t)d * Hout + u;
+        if (one) {  // written after the step's arrival
+          yv = hv;
+          y_at = yo;
+          ym_at = ymo;
+        } else {
+          if (p.y) p.y[yo] = hv;
+          if (p.ymid) reinterpret_cast<WT *>(p.ymid)[ymo] = Op<WT>::from_f(hv);
+        }
       }
     }
-    if (!proj) prefetch(step + 1);
     if (tr) p.trace[step * 16 + 1] = globaltimer_ns();
-    if (!group_barrier(ctr, ++nbar * p.NU, p.err, p.timeout_ns)) return;
+    // publish h_t first; the outputs and the next step's G loads follow the
+    // arrival, so its release does not wait for them
+    group_arrive(ctr);
+    if (one && y_at != SIZE_MAX) {
+      if (p.y) p.y[y_at] = yv;
+      if (p.ymid) reinterpret_cast<WT *>(p.ymid)[ym_at] = Op<WT>::from_f(yv);
+    }
+    if (!proj) prefetch(step + 1);
+    if (!group_wait(ctr, ++nbar * p.NU, p.err, p.timeout_ns)) return;
     if (tr) p.trace[step * 16 + 2] = globaltimer_ns();
 
     // ---- phase 2 (LSTMP): h_t = W_hr m_t for this CTA's projection rows

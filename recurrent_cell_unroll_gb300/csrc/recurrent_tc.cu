@@ -252,8 +252,8 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
         uint64_t bd = bdesc0;
         for (int kb = 0; kb < nkb; ++kb, bd += bstep) {
           const long long c0 = tr ? clock64() : 0;
+          // the stage's mbarrier (TMA complete_tx) orders its operand bytes for the MMA
           if (!tc::mbar_wait(&ctl->full[stage], phase, p.err, abort, tmo)) { ok = false; break; }
-          tc::tc_fence_after();
           const long long c1 = tr ? clock64() : 0;
           if (tr) {
             if (kb > 0) cyc_wait += c1 - c0;

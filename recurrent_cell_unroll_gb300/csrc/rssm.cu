@@ -18,6 +18,8 @@
 // disjoint batch slices and never wait on each other.
 #include <cooperative_groups.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -99,23 +101,63 @@ __device__ __forceinline__ float softplus_f(float v) {
 }
 
 // part[q][r][o] = sum over K-chunk q of Wt[k*O + o] * V[r*ldv + k], for
-// o < O, r < nr, q < ks; thread t = (o, r, q) with o fastest.
+// o < O, r < NR, q < ks.  Thread t = (o, q) with o fastest covers every row:
+// each weight is read once and used NR times, the V reads are broadcasts, and
+// the NR x 2 accumulators are independent.
+template <int NR>
 __device__ __forceinline__ void matvec_part(const float *Wt, int O, int K, const float *V,
-                                            int ldv, int nr, int ks, float *part) {
-  const int n = O * nr * ks;
+                                            int ldv, int ks, float *part) {
+  const int n = O * ks;
   const int kc = ceil_div(K, ks);
   for (int t = threadIdx.x; t < n; t += NT) {
-    const int o = t % O, r = (t / O) % nr, q = t / (O * nr);
+    const int o = t % O, q = t / O;
     const int k0 = q * kc, k1 = min(K, k0 + kc);
-    const float *v = V + (size_t)r * ldv;
-    float a0 = 0.f, a1 = 0.f;
+    float a[NR][2];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) a[r][0] = a[r][1] = 0.f;
     int k = k0;
     for (; k + 1 < k1; k += 2) {
-      a0 = fmaf(Wt[(size_t)k * O + o], v[k], a0);
-      a1 = fmaf(Wt[(size_t)(k + 1) * O + o], v[k + 1], a1);
+      const float w0 = Wt[(size_t)k * O + o], w1 = Wt[(size_t)(k + 1) * O + o];
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        a[r][0] = fmaf(w0, V[(size_t)r * ldv + k], a[r][0]);
+        a[r][1] = fmaf(w1, V[(size_t)r * ldv + k + 1], a[r][1]);
+      }
     }
-    if (k < k1) a0 = fmaf(Wt[(size_t)k * O + o], v[k], a0);
-    part[((size_t)q * nr + r) * O + o] = a0 + a1;
+    if (k < k1) {
+      const float w0 = Wt[(size_t)k * O + o];
+#pragma unroll
+      for (int r = 0; r < NR; ++r) a[r][0] = fmaf(w0, V[(size_t)r * ldv + k], a[r][0]);
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r) part[((size_t)q * NR + r) * O + o] = a[r][0] + a[r][1];
+  }
+}
+
+// Load rows [row0, row0 + n) of a row-major [rows][K] matrix, transposed into
+// shared memory dst[k * ldt + o] (o < n), zero for o in [n, ldt).  Global reads
+// are coalesced along k.
+__device__ __forceinline__ void load_T(const float *src, int K, int row0, int n, int ncols,
+                                       int ldt, float *dst) {
+  for (int e = threadIdx.x; e < ncols * K; e += NT) {
+    const int o = e / K, k = e % K;
+    dst[(size_t)k * ldt + o] = o < n ? src[(size_t)(row0 + o) * K + k] : 0.f;
+  }
+}
+
+// Split cluster barrier: stores placed between arrive and wait are not
+// ordered by this arrival's release (they are outputs nobody in the cluster
+// reads), so the release does not wait for them.
+__device__ __forceinline__ void cl_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cl_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void flush_outputs(float (&v)[3], float *(&ptr)[3], int n) {
+  for (int i = 0; i < n; ++i) {
+    if (ptr[i]) *ptr[i] = v[i];
+    ptr[i] = nullptr;
   }
 }
 
@@ -125,6 +167,7 @@ __device__ __forceinline__ float part_sum(const float *part, int O, int nr, int 
   return a;
 }
 
+template <int NR>
 __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
     rssm_kernel(const RssmParams p, int Bc) {
   extern __shared__ __align__(16) float sm[];
@@ -140,37 +183,26 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
   const int j0 = c * d.Ua, nj = max(0, min(d.Ua, RH - j0));   // owned GRU units
   const int s0 = c * d.Sa, ns = max(0, min(d.Sa, S - s0));    // owned state entries
   const int tid = threadIdx.x;
+  const bool tr = p.trace && blockIdx.x == 0 && tid == 0;
+  if (tr) p.trace[11] = globaltimer_ns();
 
   // ---- resident weights, transposed to [k][o]; rows of outputs not owned are zero
-  for (int e = tid; e < SA * d.Ha; e += NT) {
-    const int k = e / d.Ha, o = e % d.Ha;
-    sm[L.w1 + e] = o < ni ? p.W1[(size_t)(i0 + o) * SA + k] : 0.f;
-  }
+  load_T(p.W1, SA, i0, ni, d.Ha, d.Ha, sm + L.w1);
   for (int o = tid; o < d.Ha; o += NT) {
     sm[L.b1 + o] = (o < ni && p.b1) ? p.b1[i0 + o] : 0.f;
     sm[L.b2 + o] = (o < ni && p.b2) ? p.b2[i0 + o] : 0.f;
   }
-  for (int e = tid; e < Hd * 3 * d.Ua; e += NT) {
-    const int k = e / (3 * d.Ua), o = e % (3 * d.Ua), g = o / d.Ua, j = o % d.Ua;
-    sm[L.wih + e] = j < nj ? p.Wih[(size_t)(g * RH + j0 + j) * Hd + k] : 0.f;
-  }
-  for (int e = tid; e < RH * 3 * d.Ua; e += NT) {
-    const int k = e / (3 * d.Ua), o = e % (3 * d.Ua), g = o / d.Ua, j = o % d.Ua;
-    sm[L.whh + e] = j < nj ? p.Whh[(size_t)(g * RH + j0 + j) * RH + k] : 0.f;
+  for (int g = 0; g < 3; ++g) {
+    load_T(p.Wih, Hd, g * RH + j0, nj, d.Ua, 3 * d.Ua, sm + L.wih + g * d.Ua);
+    load_T(p.Whh, RH, g * RH + j0, nj, d.Ua, 3 * d.Ua, sm + L.whh + g * d.Ua);
   }
   for (int o = tid; o < 3 * d.Ua; o += NT) {
     const int g = o / d.Ua, j = o % d.Ua;
     sm[L.bih + o] = (j < nj && p.bih) ? p.bih[g * RH + j0 + j] : 0.f;
     sm[L.bhh + o] = (j < nj && p.bhh) ? p.bhh[g * RH + j0 + j] : 0.f;
   }
-  for (int e = tid; e < RH * d.Ha; e += NT) {
-    const int k = e / d.Ha, o = e % d.Ha;
-    sm[L.w2 + e] = o < ni ? p.W2[(size_t)(i0 + o) * RH + k] : 0.f;
-  }
-  for (int e = tid; e < Hd * 2 * d.Sa; e += NT) {
-    const int k = e / (2 * d.Sa), o = e % (2 * d.Sa), h = o / d.Sa, j = o % d.Sa;
-    sm[L.w3 + e] = j < ns ? p.W3[(size_t)(h * S + s0 + j) * Hd + k] : 0.f;
-  }
+  load_T(p.W2, RH, i0, ni, d.Ha, d.Ha, sm + L.w2);
+  for (int h = 0; h < 2; ++h) load_T(p.W3, Hd, h * S + s0, ns, d.Sa, 2 * d.Sa, sm + L.w3 + h * d.Sa);
   for (int o = tid; o < 2 * d.Sa; o += NT) {
     const int h = o / d.Sa, j = o % d.Sa;
     sm[L.b3 + o] = (j < ns && p.b3) ? p.b3[h * S + s0 + j] : 0.f;
@@ -196,19 +228,23 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
     }
   }
   cluster.sync();
+  if (tr) p.trace[12] = globaltimer_ns();
 
   float *rem[RC];
 #pragma unroll
   for (int r = 0; r < RC; ++r) rem[r] = cluster.map_shared_rank(sm, r);
 
   const int ks1 = split_of(d.Ha, Bc, SA);
-  const int ks2a = split_of(3 * d.Ua, Bc, Hd), ks2b = split_of(3 * d.Ua, Bc, RH);
-  const int ks3 = split_of(d.Ha, Bc, RH);
-  const int ks4 = split_of(2 * d.Sa, Bc, Hd);
+  const int ks2a = split_of(3 * d.Ua, 1, Hd), ks2b = split_of(3 * d.Ua, 1, RH);
+  const int ks3 = split_of(d.Ha, 1, RH);
+  const int ks4 = split_of(2 * d.Sa, 1, Hd);
   float *part1 = sm + L.part1, *part2 = sm + L.part2;
+  float out_v[3] = {0.f, 0.f, 0.f};
+  float *out_p[3] = {nullptr, nullptr, nullptr};
 
   for (int t = 0; t < p.T; ++t) {
     const int cur = t & 1;
+    if (tr) p.trace[t * 16 + 0] = globaltimer_ns();
     float *bel_cur = sm + L.bel + (size_t)cur * Bc * RH;
     const size_t bel_nxt = L.bel + (size_t)(cur ^ 1) * Bc * RH;
     // ---- phase 1: a = ELU(W1 [state, action] + b1), owned outputs.
@@ -229,6 +265,7 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
         part1[((size_t)qq * Bc + r) * O + o] = a;
       }
       __syncthreads();
+      if (tr) p.trace[t * 16 + 10] = clock64();
       for (int e = tid; e < ni * Bc; e += NT) {
         const int o = e % ni, r = e / ni;
         const float a = elu_f(part_sum(part1, O, Bc, ks1, r, o) + sm[L.b1 + o]);
@@ -237,10 +274,13 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
       }
     }
     cluster.sync();
+    if (tr) p.trace[t * 16 + 1] = globaltimer_ns();
     // ---- phase 2: GRUCell(a, belief) for owned units
-    matvec_part(sm + L.wih, 3 * d.Ua, Hd, sm + L.av, Hd, Bc, ks2a, part1);
-    matvec_part(sm + L.whh, 3 * d.Ua, RH, bel_cur, RH, Bc, ks2b, part2);
+    const long long c2 = clock64();
+    matvec_part<NR>(sm + L.wih, 3 * d.Ua, Hd, sm + L.av, Hd, ks2a, part1);
+    matvec_part<NR>(sm + L.whh, 3 * d.Ua, RH, bel_cur, RH, ks2b, part2);
     __syncthreads();
+    if (tr) p.trace[t * 16 + 8] = clock64() - c2;
     for (int e = tid; e < nj * Bc; e += NT) {
       const int j = e % nj, r = e / nj;
       const int O = 3 * d.Ua;
@@ -256,11 +296,19 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
       const float hb = (1.f - zg) * ng + zg * bel_cur[(size_t)r * RH + j0 + j];
 #pragma unroll
       for (int x = 0; x < RC; ++x) rem[x][bel_nxt + (size_t)r * RH + j0 + j] = hb;
-      if (r < nr) p.beliefs[((size_t)t * p.B + b0 + r) * RH + j0 + j] = hb;
+      if (r < nr) {
+        float *dst = p.beliefs + ((size_t)t * p.B + b0 + r) * RH + j0 + j;
+        if (e == tid) { out_v[0] = hb; out_p[0] = dst; }  // stored after the arrival
+        else *dst = hb;
+      }
     }
-    cluster.sync();
+    if (tr) p.trace[t * 16 + 9] = clock64() - c2;
+    cl_arrive();
+    flush_outputs(out_v, out_p, 1);
+    cl_wait();
+    if (tr) p.trace[t * 16 + 2] = globaltimer_ns();
     // ---- phase 3: q = ELU(W2 belief + b2), owned outputs
-    matvec_part(sm + L.w2, d.Ha, RH, sm + bel_nxt, RH, Bc, ks3, part1);
+    matvec_part<NR>(sm + L.w2, d.Ha, RH, sm + bel_nxt, RH, ks3, part1);
     __syncthreads();
     for (int e = tid; e < ni * Bc; e += NT) {
       const int o = e % ni, r = e / ni;
@@ -269,8 +317,9 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
       for (int x = 0; x < RC; ++x) rem[x][L.qv + (size_t)r * Hd + i0 + o] = qv;
     }
     cluster.sync();
+    if (tr) p.trace[t * 16 + 3] = globaltimer_ns();
     // ---- phase 4: p = W3 q + b3 -> mean, std, sampled state (owned entries)
-    matvec_part(sm + L.w3, 2 * d.Sa, Hd, sm + L.qv, Hd, Bc, ks4, part1);
+    matvec_part<NR>(sm + L.w3, 2 * d.Sa, Hd, sm + L.qv, Hd, ks4, part1);
     __syncthreads();
     for (int e = tid; e < ns * Bc; e += NT) {
       const int j = e % ns, r = e / ns;
@@ -282,14 +331,23 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
         const size_t o = ((size_t)t * p.B + b0 + r) * S + s0 + j;
         const float ev = L.preload ? sm[L.eps + ((size_t)t * Bc + r) * S + s0 + j] : __ldg(p.eps + o);
         st = fmaf(ev, sd, mean);
-        p.means[o] = mean;
-        p.stds[o] = sd;
-        p.states[o] = st;
+        if (e == tid) {  // stored after the arrival
+          out_v[0] = mean; out_p[0] = p.means + o;
+          out_v[1] = sd; out_p[1] = p.stds + o;
+          out_v[2] = st; out_p[2] = p.states + o;
+        } else {
+          p.means[o] = mean;
+          p.stds[o] = sd;
+          p.states[o] = st;
+        }
       }
 #pragma unroll
       for (int x = 0; x < RC; ++x) rem[x][L.st + (size_t)r * S + s0 + j] = st;
     }
-    cluster.sync();
+    cl_arrive();
+    flush_outputs(out_v, out_p, 3);
+    cl_wait();
+    if (tr) p.trace[t * 16 + 4] = globaltimer_ns();
   }
 }
 
@@ -300,6 +358,15 @@ int pick_bc(int B, int nsm) {
   if (bc < 1) bc = 1;
   if (bc > MAXBC) bc = MAXBC;
   return bc;
+}
+
+template <int NR>
+cudaError_t launch_nr(const RssmParams &p, int Bc, int grid, size_t smem, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute((const void *)rssm_kernel<NR>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  rssm_kernel<NR><<<grid, NT, smem, s>>>(p, Bc);
+  return cudaGetLastError();
 }
 
 size_t smem_bytes(int S, int A, int Hd, int RH, int Bc, int T) {
@@ -313,18 +380,68 @@ bool rssm_supported(int S, int A, int Hd, int RH) {
   return smem_bytes(S, A, Hd, RH, 1, 0) <= 227 * 1024;
 }
 
+// Clusters of RC CTAs that can be resident at once with this shared-memory
+// size (a cluster needs RC free SMs in one GPC, so this is below nsm / RC).
+int resident_clusters(size_t smem, int Bc, int nsm) {
+  const void *fn;
+  switch (Bc) {
+    case 1: fn = (const void *)rssm_kernel<1>; break;
+    case 2: fn = (const void *)rssm_kernel<2>; break;
+    case 3: fn = (const void *)rssm_kernel<3>; break;
+    case 4: fn = (const void *)rssm_kernel<4>; break;
+    case 5: fn = (const void *)rssm_kernel<5>; break;
+    case 6: fn = (const void *)rssm_kernel<6>; break;
+    case 7: fn = (const void *)rssm_kernel<7>; break;
+    default: fn = (const void *)rssm_kernel<8>; break;
+  }
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return std::max(1, nsm / RC);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(RC);
+  cfg.blockDim = dim3(NT);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = RC;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    return std::max(1, nsm / RC);
+  }
+  return n;
+}
+
 cudaError_t launch_rssm(const RssmParams &p, int nsm, cudaStream_t s, int *clusters_used) {
   int Bc = pick_bc(p.B, nsm);
   while (Bc > 1 && smem_bytes(p.S, p.A, p.Hd, p.RH, Bc, p.T) > 227 * 1024) --Bc;
+  // all clusters should be resident together: grow the batch slice until they are
+  for (int it = 0; it < MAXBC; ++it) {
+    const int room = resident_clusters(smem_bytes(p.S, p.A, p.Hd, p.RH, Bc, p.T), Bc, nsm);
+    if (ceil_div(p.B, Bc) <= room || Bc >= MAXBC) break;
+    if (smem_bytes(p.S, p.A, p.Hd, p.RH, Bc + 1, p.T) > 227 * 1024) break;
+    ++Bc;
+  }
   const size_t smem = smem_bytes(p.S, p.A, p.Hd, p.RH, Bc, p.T);
   if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
   const int clusters = ceil_div(p.B, Bc);
   if (clusters_used) *clusters_used = clusters;
-  cudaError_t e = cudaFuncSetAttribute((const void *)rssm_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  rssm_kernel<<<clusters * RC, NT, smem, s>>>(p, Bc);
-  return cudaGetLastError();
+  switch (Bc) {
+    case 1: return launch_nr<1>(p, Bc, clusters * RC, smem, s);
+    case 2: return launch_nr<2>(p, Bc, clusters * RC, smem, s);
+    case 3: return launch_nr<3>(p, Bc, clusters * RC, smem, s);
+    case 4: return launch_nr<4>(p, Bc, clusters * RC, smem, s);
+    case 5: return launch_nr<5>(p, Bc, clusters * RC, smem, s);
+    case 6: return launch_nr<6>(p, Bc, clusters * RC, smem, s);
+    case 7: return launch_nr<7>(p, Bc, clusters * RC, smem, s);
+    default: return launch_nr<8>(p, Bc, clusters * RC, smem, s);
+  }
 }
 
 }  // namespace rcu
