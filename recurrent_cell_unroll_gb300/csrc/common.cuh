@@ -53,19 +53,10 @@ template <> struct Op<__nv_bfloat16> {
   __device__ __forceinline__ static __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
 };
 
-// Bounded group barrier over `n` CTAs sharing counter `ctr` (monotone; the
-// k-th barrier waits for k*n arrivals).  Every wait is bounded by
-// `timeout_ns` on the global timer and by the shared error word: a CTA that
-// times out records DEV_TIMEOUT and every CTA then leaves its step loop.
-// Returns false when the kernel must stop.
-// Ordering: the CTA's writes precede thread 0's arrival through
-// __syncthreads, and the arrival is a release at GPU scope (cumulative), so
-// no separate full fence is needed; the waiting side reads with acquire and
-// passes the ordering on through __syncthreads.  Data exchanged this way is
-// read with L1-bypassing loads.
-// Split form of group_barrier: group_arrive publishes the CTA's writes made
-// so far; work placed between the two calls (output stores, loads of the
-// next step's inputs) is not waited for by this arrival's release.
+// Split form of group_barrier (below): group_arrive publishes the CTA's
+// writes made so far; work placed between the two calls (output stores,
+// loads of the next step's inputs) is not waited for by this arrival's
+// release.  group_wait is bounded exactly like group_barrier.
 __device__ __forceinline__ void group_arrive(unsigned *ctr, bool skip_arrive = false) {
   __syncthreads();
   if (threadIdx.x == 0 && !skip_arrive) red_release_gpu_add(ctr, 1u);
@@ -91,6 +82,16 @@ __device__ __forceinline__ bool group_wait(unsigned *ctr, unsigned target, int *
   return s_ok2 != 0;
 }
 
+// Bounded group barrier over `n` CTAs sharing counter `ctr` (monotone; the
+// k-th barrier waits for k*n arrivals).  Every wait is bounded by
+// `timeout_ns` on the global timer and by the shared error word: a CTA that
+// times out records DEV_TIMEOUT and every CTA then leaves its step loop.
+// Returns false when the kernel must stop.
+// Ordering: the CTA's writes precede thread 0's arrival through
+// __syncthreads, and the arrival is a release at GPU scope (cumulative), so
+// no separate full fence is needed; the waiting side reads with acquire and
+// passes the ordering on through __syncthreads.  Data exchanged this way is
+// read with L1-bypassing loads.
 __device__ __forceinline__ bool group_barrier(unsigned *ctr, unsigned target, int *err,
                                               uint64_t timeout_ns, bool skip_arrive = false) {
   __syncthreads();

@@ -265,14 +265,15 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
             }
           }
           const uint64_t ad = adesc0 + (uint64_t)(stage * (A_STAGE >> 4));
-          tc::mma_bf16(tbase, ad, bd, idesc, kb != 0);
-          tc::mma_bf16(tbase, ad + 2, bd + 2, idesc, 1u);
-          tc::mma_bf16(tbase, ad + 4, bd + 4, idesc, 1u);
-          tc::mma_bf16(tbase, ad + 6, bd + 6, idesc, 1u);
-          if (cs == 1)
-            tc::mma_commit(&ctl->empty[stage]);
-          else
+          if (cs == 1) {
+            tc::mma4_bf16_commit(tbase, ad, bd, idesc, kb != 0, &ctl->empty[stage]);
+          } else {
+            tc::mma_bf16(tbase, ad, bd, idesc, kb != 0);
+            tc::mma_bf16(tbase, ad + 2, bd + 2, idesc, 1u);
+            tc::mma_bf16(tbase, ad + 4, bd + 4, idesc, 1u);
+            tc::mma_bf16(tbase, ad + 6, bd + 6, idesc, 1u);
             tc::mma_commit_mc(&ctl->empty[stage], cmask);
+          }
           if (tr) cyc_issue += clock64() - c1;
           if (++stage == STG) { stage = 0; phase ^= 1; }
         }

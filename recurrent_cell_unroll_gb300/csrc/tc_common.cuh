@@ -149,6 +149,27 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
       : "memory");
 }
 
+// Four K=16 MMAs over one 64-wide K block (descriptors advanced by 32 bytes,
+// i.e. +2 in the start-address field) followed by a commit to `bar`, as one
+// instruction sequence: nothing the compiler schedules sits between the MMAs.
+__device__ __forceinline__ void mma4_bf16_commit(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t accumulate,
+                                                 uint64_t *bar) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.u32 t, 1, 1;\n\t"
+      "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+      "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, t;\n\t"
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t}" ::"r"(
+          tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Arrive once on the mbarrier at `bar`'s offset in every CTA of `mask` when
 // all previously issued tcgen05.mma of this thread complete.
 __device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t mask) {
