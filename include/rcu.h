@@ -78,6 +78,11 @@ typedef struct rcu_rssm_s *rcu_rssm_t;
                                          cluster that share each h tile by TMA multicast
                                          (0 or 1 = none, 2, 4, 8; used when it divides the
                                          number of unit groups) */
+#define RCU_ATTR_TC_KSPLIT 7          /* tensor-core recurrent kernel: CTAs that split the
+                                         K (= hidden) dimension of h W_hh^T, exchanging
+                                         partial sums through distributed shared memory
+                                         (0 = automatic: 2 where it fits, 1 = no split,
+                                         2 = CTA pairs) */
 #define RCU_ATTR_PROFILE 4            /* 1 = record a CUDA event pair around every kernel
                                          this handle launches (on the launching stream);
                                          read the totals with rnn_profile_entry */
@@ -182,8 +187,10 @@ RCU_API int rnn_profile_reset(rcu_rnn_t h);
  * (ns) of CTA 0 are copied to host_out[t*16 .. t*16+15] (0 where a slot is
  * unused).  Tensor-core kernel slots: 0 producer saw the step barrier,
  * 1 first h stage landed, 8 last h stage landed, 2 last MMA issued,
- * 3 epilogue got the accumulator, 5 accumulator read, 6 gates done and h_t
- * stored, 7 epilogue threads joined, 4 h_t published.  Portable kernel
+ * 3 epilogue got the accumulator, 5 accumulator read, 11 partner CTA's
+ * partial sums received (K split only), 6 gates done and h_t stored,
+ * 7 epilogue threads joined, 4 h_t published; slots 9 and 10 hold the MMA
+ * thread's clock cycles spent waiting for and issuing h stages.  Portable kernel
  * slots: 0 step start, 1 gates done, 2 barrier passed.  Synchronises the
  * stream.  host_out is host memory.
  */

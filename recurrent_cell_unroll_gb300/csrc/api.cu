@@ -127,6 +127,7 @@ struct rcu_rnn_s {
   int drop_arrival = 0;
   int force_path = 0;
   int tc_cluster = 0;  // CTAs per cluster sharing h loads in the tensor-core recurrent kernel
+  int tc_ksplit = 0;   // CTAs splitting K in the tensor-core recurrent kernel (0 = automatic)
   int launches = 0;
   bool used_tc_gemm = false, used_tc_rec = false;
   // opt-in per-step trace of the first layer's recurrent kernel
@@ -269,6 +270,10 @@ extern "C" int rnn_set_attr(rcu_rnn_t h, int attr, int64_t value) {
       if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8)
         return fail(RCU_ERR_INVALID, "cluster size must be 0, 1, 2, 4 or 8");
       h->tc_cluster = (int)value;
+      return RCU_OK;
+    case RCU_ATTR_TC_KSPLIT:
+      if (value < 0 || value > 2) return fail(RCU_ERR_INVALID, "K split must be 0, 1 or 2");
+      h->tc_ksplit = (int)value;
       return RCU_OK;
     case RCU_ATTR_TRACE:
       h->trace = value != 0;
@@ -600,6 +605,7 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
       TcRecParams tp;
       tp.base = pf;
       tp.cluster = h->tc_cluster;
+      tp.ksplit = h->tc_ksplit;
       for (int d = 0; d < D; ++d) tp.Wtc[d] = h->lw[(size_t)l * D + d].fold_w.p;
       h->begin("recurrent_tc_lstmp", s);
       cudaError_t e = launch_tc_recurrent(tp, h->nsm, s);
@@ -643,6 +649,7 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
       TcRecParams tp;
       tp.base = p;
       tp.cluster = h->tc_cluster;
+      tp.ksplit = h->tc_ksplit;
       for (int d = 0; d < D; ++d) tp.Wtc[d] = h->lw[(size_t)l * D + d].tc_whh.p;
       cudaError_t e = launch_tc_recurrent(tp, h->nsm, s);
       if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "tc recurrent: %s", cudaGetErrorString(e));

@@ -31,7 +31,7 @@ namespace rcu {
 
 namespace {
 
-constexpr int UNITS = 16;       // hidden units per CTA
+constexpr int UNITS = 16;       // hidden units each CTA finalises
 constexpr int BG = 128;         // batch rows per CTA (MMA M)
 constexpr int BK = 64;          // K per stage (128 bytes of bf16)
 constexpr int A_STAGE = BG * BK * 2;
@@ -43,45 +43,41 @@ constexpr int MAX_STAGES = 8;
 
 struct Maps {
   CUtensorMap hx;    // [D*2*B rows][K cols], ld Kp, bf16, box 64 x 128
-  CUtensorMap w[2];  // per direction [NU*N rows][K cols], ld Kp, bf16, box 64 x N
+  CUtensorMap w[2];  // per direction [NU16*nG*16 rows][K cols], ld Kp, bf16, box 64 x N
 };
 
 struct Ctl {
-  uint64_t full[MAX_STAGES], empty[MAX_STAGES], wbar, tfull, tfree, mdone;
+  uint64_t full[MAX_STAGES], empty[MAX_STAGES], wbar, tfull, tfree, mdone, xfull;
   uint32_t tmem_base;
   int abort;
-  int go;  // epilogue: result of the per-step accumulator wait, shared by all 128 threads
+  int go;   // epilogue: result of the per-step accumulator wait, shared by all its threads
+  int go2;  // epilogue: result of the per-step partial-sum wait (K split)
+  uint32_t x_sent;  // K split: steps whose partial sums this CTA has sent to its peer
 };
 
+// KS = CTAs splitting K (a cluster of KS CTAs computes the gate
+// pre-activations of 16*KS units for 128 rows; each CTA accumulates its 1/KS
+// of K over all 16*KS units, then each finalises 16 of them after the
+// partial sums for its units have been exchanged through distributed shared
+// memory).
 struct Geo {
-  int N, nkb, stages;
-  size_t w_bytes, smem;
+  int N, nkb, nkbm, stages;
+  size_t w_bytes, x_bytes, smem;
 };
 
-__host__ __device__ inline Geo make_geo(int nG, int K) {
+__host__ __device__ inline Geo make_geo(int nG, int K, int KS) {
   Geo g;
-  g.N = nG * UNITS;
+  g.N = nG * UNITS * KS;
   g.nkb = ceil_div(K, BK);
-  g.w_bytes = (size_t)g.nkb * g.N * 128;
-  const size_t fixed = 1024 + g.w_bytes + 256;
+  g.nkbm = ceil_div(g.nkb, KS);
+  g.w_bytes = (size_t)g.nkbm * g.N * 128;
+  // partial sums received from the other KS-1 CTAs: [KS-1][nG][4][128] float4
+  g.x_bytes = (size_t)(KS - 1) * nG * 4 * BG * 16;
+  const size_t fixed = 1024 + g.w_bytes + g.x_bytes + 256;
   int st = (int)((SMEM_LIMIT - (long long)fixed) / A_STAGE);
   g.stages = st > MAX_STAGES ? MAX_STAGES : st;
   g.smem = fixed + (size_t)(g.stages > 0 ? g.stages : 0) * A_STAGE;
   return g;
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void fence_proxy_async_global() {
@@ -91,15 +87,14 @@ __device__ __forceinline__ void epi_bar() {
   asm volatile("bar.sync 1, %0;" ::"n"(32 * EPI_WARPS) : "memory");
 }
 
-// 32 lanes x 4 consecutive 32-bit TMEM columns
-__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
-  uint32_t r[4];
+// 32 lanes x 4 consecutive 32-bit TMEM columns (no wait)
+__device__ __forceinline__ void tmem_ld4_nowait(uint32_t taddr, uint32_t (&r)[4]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // bf16 path activations on the MUFU tanh unit (PTX tanh.approx.f32); the
@@ -111,31 +106,31 @@ __device__ __forceinline__ float tanh_fast(float x) {
 }
 __device__ __forceinline__ float sigmoid_fast(float x) { return fmaf(0.5f, tanh_fast(0.5f * x), 0.5f); }
 
-__device__ __forceinline__ void load16(const float *p, float (&v)[16]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float4 f = __ldg(reinterpret_cast<const float4 *>(p) + i);
-    v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
-  }
-}
-
-template <int NG>
+template <int NG, int KS>
 __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ Maps maps,
                                                        const RecParams p) {
+  static_assert(KS == 1 || KS == 2, "K is split over one or two CTAs");
+  constexpr int NTOT = NG * UNITS * KS;
+  constexpr uint32_t TCOLS = NTOT <= 64 ? 64 : (NTOT <= 128 ? 128 : 256);
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
-  const Geo geo = make_geo(NG, p.Hout);
-  const int N = geo.N, nkb = geo.nkb, STG = geo.stages;
-  uint8_t *sW = smem;                       // resident B operand, nkb blocks of N x 128 B
+  const Geo geo = make_geo(NG, p.Hout, KS);
+  const int N = geo.N, STG = geo.stages;
+  uint8_t *sW = smem;                       // resident B operand, nkbm blocks of N x 128 B
   uint8_t *sA = smem + geo.w_bytes;         // ring of STG stages of 128 x 128 B
-  Ctl *ctl = reinterpret_cast<Ctl *>(sA + (size_t)STG * A_STAGE);
+  float4 *xbuf = reinterpret_cast<float4 *>(sA + (size_t)STG * A_STAGE);
+  Ctl *ctl = reinterpret_cast<Ctl *>(reinterpret_cast<uint8_t *>(xbuf) + geo.x_bytes);
 
-  const int NU = p.NU, NBG = ceil_div(p.B, BG);
+  const int NU = p.NU, NBG = ceil_div(p.B, BG);  // NU = CTAs per (direction, batch group)
   const int d = blockIdx.x / (NBG * NU);
   const int rem = blockIdx.x % (NBG * NU);
-  const int bg = rem / NU, ug = rem % NU;
-  const int u0 = ug * UNITS, row0 = bg * BG;
+  const int bg = rem / NU, cu = rem % NU;
+  const int kr = KS > 1 ? cu % KS : 0;          // this CTA's K share (= rank in its cluster)
+  const int ugc = cu / KS;                      // unit group of the cluster (16*KS units)
+  const int u0 = ugc * UNITS * KS + kr * UNITS, row0 = bg * BG;
+  const int kb0 = kr * geo.nkbm;
+  const int nk = min(geo.nkb, kb0 + geo.nkbm) - kb0;  // K blocks of this CTA (>= 1)
   const int B = p.B, H = p.H, Kp = p.Kp;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   volatile int *abort = &ctl->abort;
@@ -143,10 +138,11 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
   unsigned *ctr = p.ctr + d * NBG + bg;
   // steps this batch group runs: the longest row of the group (rows sorted by length)
   const int Tg = row0 < B ? p.meta.lens_sorted[row0] : 0;
-  // cluster of CTAs sharing (d, bg): each issues 1/cs of the h k-blocks as
-  // multicast loads into every member; a stage is free again once all
-  // members' MMAs have consumed it
-  const uint32_t cs = tc::cluster_nctarank(), crank = tc::cluster_ctarank();
+  // without a K split, an optional cluster of CTAs sharing (d, bg): each
+  // issues 1/cs of the h k-blocks as multicast loads into every member; a
+  // stage is free again once all members' MMAs have consumed it
+  const uint32_t cs = KS > 1 ? 1u : tc::cluster_nctarank();
+  const uint32_t crank = KS > 1 ? 0u : tc::cluster_ctarank();
   const uint16_t cmask = (uint16_t)((1u << cs) - 1u);
 
   if (threadIdx.x == 0) {
@@ -158,24 +154,31 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
     tc::mbar_init(&ctl->tfull, 1);
     tc::mbar_init(&ctl->tfree, EPI_WARPS);
     tc::mbar_init(&ctl->mdone, 1);
+    // partial sums from the peer: this CTA's own arrival with the expected
+    // byte count, completed by the peer's asynchronous stores
+    tc::mbar_init(&ctl->xfull, 1);
     ctl->abort = 0;
+    ctl->x_sent = 0;
     tc::fence_mbar_init();
   }
-  if (warp == 1) tc::tmem_alloc(&ctl->tmem_base, 64);
+  if (warp == 1) tc::tmem_alloc(&ctl->tmem_base, TCOLS);
   tc::tc_fence_before();
   __syncthreads();
-  if (cs > 1) tc::cluster_sync();  // peers' barriers exist before any multicast
+  // peers' barriers exist before any multicast load or partial-sum store
+  if (cs > 1 || KS > 1) tc::cluster_sync();
   tc::tc_fence_after();
   const uint32_t tbase = ctl->tmem_base;
+  int x_left = 0;  // K split, thread 64: phases consumed (negated - 1 if one more is armed)
 
   if (warp == 0) {
     if (lane == 0) {
       tc::prefetch_tmap(&maps.hx);
       tc::prefetch_tmap(&maps.w[d]);
-      // resident weights: rows [ug*N, ug*N + N) of this direction's packed W_hh
-      tc::mbar_arrive_expect_tx(&ctl->wbar, (uint32_t)geo.w_bytes);
-      for (int kb = 0; kb < nkb; ++kb)
-        tc::tma_load_2d(sW + (size_t)kb * N * 128, &maps.w[d], &ctl->wbar, kb * BK, ug * N);
+      // resident weights: rows [ugc*N, ugc*N + N) of this direction's packed
+      // W_hh (rows past the packed tensor read as zero), K blocks [kb0, kb0+nk)
+      tc::mbar_arrive_expect_tx(&ctl->wbar, (uint32_t)(nk * N * 128));
+      for (int i = 0; i < nk; ++i)
+        tc::tma_load_2d(sW + (size_t)i * N * 128, &maps.w[d], &ctl->wbar, (kb0 + i) * BK, ugc * N);
       int stage = 0;
       uint32_t phase = 0;
       int pend_stage[MAX_STAGES], npend = 0;
@@ -202,7 +205,8 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
         fence_proxy_async_global();
         if (p.trace && blockIdx.x == 0) p.trace[step * 16 + 0] = globaltimer_ns();
         const int arow = (d * 2 + (step & 1)) * B + row0;
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int i = 0; i < nk; ++i) {
+          const int kb = kb0 + i;
           if (!tc::mbar_wait(&ctl->empty[stage], phase ^ 1, p.err, abort, tmo)) goto producer_out;
           tc::mbar_arrive_expect_tx(&ctl->full[stage], A_STAGE);
           if (cs == 1) {
@@ -233,7 +237,7 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = tc::idesc_bf16_f32(BG, NG * UNITS);
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(BG, NTOT);
       // The issuing thread is on the critical path: descriptors are built once
       // and advanced by adding (byte offset >> 4) to the start-address field
       // (all shared-memory offsets here stay below 256 KB, so the 14-bit
@@ -250,15 +254,15 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
         tc::tc_fence_after();
         long long cyc_wait = 0, cyc_issue = 0;
         uint64_t bd = bdesc0;
-        for (int kb = 0; kb < nkb; ++kb, bd += bstep) {
+        for (int i = 0; i < nk; ++i, bd += bstep) {
           const long long c0 = tr ? clock64() : 0;
           // the stage's mbarrier (TMA complete_tx) orders its operand bytes for the MMA
           if (!tc::mbar_wait(&ctl->full[stage], phase, p.err, abort, tmo)) { ok = false; break; }
           const long long c1 = tr ? clock64() : 0;
           if (tr) {
-            if (kb > 0) cyc_wait += c1 - c0;
-            if (kb == 0) p.trace[step * 16 + 1] = globaltimer_ns();
-            if (kb == nkb - 1) {
+            if (i > 0) cyc_wait += c1 - c0;
+            if (i == 0) p.trace[step * 16 + 1] = globaltimer_ns();
+            if (i == nk - 1) {
               p.trace[step * 16 + 8] = globaltimer_ns();
               p.trace[step * 16 + 9] = cyc_wait;
               p.trace[step * 16 + 10] = cyc_issue;
@@ -266,9 +270,9 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
           }
           const uint64_t ad = adesc0 + (uint64_t)(stage * (A_STAGE >> 4));
           if (cs == 1) {
-            tc::mma4_bf16_commit(tbase, ad, bd, idesc, kb != 0, &ctl->empty[stage]);
+            tc::mma4_bf16_commit(tbase, ad, bd, idesc, i != 0, &ctl->empty[stage]);
           } else {
-            tc::mma_bf16(tbase, ad, bd, idesc, kb != 0);
+            tc::mma_bf16(tbase, ad, bd, idesc, i != 0);
             tc::mma_bf16(tbase, ad + 2, bd + 2, idesc, 1u);
             tc::mma_bf16(tbase, ad + 4, bd + 4, idesc, 1u);
             tc::mma_bf16(tbase, ad + 6, bd + 6, idesc, 1u);
@@ -302,6 +306,18 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
     const bool vec_g = nu == UPT && (H & 3) == 0;
     const bool vec_y = nu == UPT && (p.Hout & 3) == 0 &&
                        (reinterpret_cast<uintptr_t>(p.y) & 15) == 0;
+    // TMEM columns: [owner CTA][gate][16 units]; lane quarter q of the warp
+    const uint32_t tl = tbase + ((uint32_t)(q * 32) << 16);
+    const uint32_t own_col = (uint32_t)(kr * NG * UNITS + part * UPT);
+    const uint32_t peer_col = (uint32_t)((1 - kr) * NG * UNITS + part * UPT);  // KS == 2
+    // partial sums for the peer's units go to the same offset of its buffer:
+    // slot (g*4 + part)*128 + r, one float4 per (gate, thread)
+    uint32_t peer_x = 0, peer_bar = 0;
+    if (KS > 1) {
+      peer_x = tc::mapa_shared(tc::smem_u32(xbuf), (uint32_t)(1 - kr));
+      peer_bar = tc::mapa_shared(tc::smem_u32(&ctl->xfull), (uint32_t)(1 - kr));
+    }
+    int x_posted = 0, x_done = 0;  // K split, thread 64: phases armed / completed
     float h[UPT], c[UPT], bn[UPT];
     int b = 0, len = 0;
     if (row_ok) {
@@ -352,12 +368,53 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
       tc::tc_fence_after();
       if (p.trace && blockIdx.x == 0 && threadIdx.x == 64) p.trace[step * 16 + 3] = globaltimer_ns();
       float acc[NG][UPT];
+      {
+        uint32_t ra[NG][4], rp[KS > 1 ? NG : 1][4];
 #pragma unroll
-      for (int g = 0; g < NG; ++g)
-        tmem_ld4(tbase + (uint32_t)(g * UNITS + part * UPT) + ((uint32_t)(q * 32) << 16), acc[g]);
-      tc::tc_fence_before();
-      if (lane == 0) tc::mbar_arrive(&ctl->tfree);
+        for (int g = 0; g < NG; ++g) tmem_ld4_nowait(tl + own_col + (uint32_t)(g * UNITS), ra[g]);
+        if (KS > 1) {
+#pragma unroll
+          for (int g = 0; g < NG; ++g)
+            tmem_ld4_nowait(tl + peer_col + (uint32_t)(g * UNITS), rp[KS > 1 ? g : 0]);
+        }
+        tmem_wait_ld();
+        tc::tc_fence_before();
+        if (lane == 0) tc::mbar_arrive(&ctl->tfree);
+        if (p.trace && blockIdx.x == 0 && threadIdx.x == 64) p.trace[step * 16 + 12] = globaltimer_ns();
+#pragma unroll
+        for (int g = 0; g < NG; ++g)
+#pragma unroll
+          for (int j = 0; j < UPT; ++j) acc[g][j] = __uint_as_float(ra[g][j]);
+        if (KS > 1) {
+          // hand the peer its units' partial sums over K blocks [kb0, kb0+nk)
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            const int gi = KS > 1 ? g : 0;
+            tc::st_async_v4(peer_x + (uint32_t)(((g * 4 + part) * BG + r) * 16),
+                            __uint_as_float(rp[gi][0]), __uint_as_float(rp[gi][1]),
+                            __uint_as_float(rp[gi][2]), __uint_as_float(rp[gi][3]), peer_bar);
+          }
+          if (threadIdx.x == 64) ctl->x_sent = (uint32_t)(step + 1);
+        }
+      }
       if (p.trace && blockIdx.x == 0 && threadIdx.x == 64) p.trace[step * 16 + 5] = globaltimer_ns();
+      if (KS > 1) {
+        // the peer's partial sums for this CTA's units
+        if (threadIdx.x == 64) {
+          tc::mbar_arrive_expect_tx(&ctl->xfull, (uint32_t)geo.x_bytes);
+          x_posted = step + 1;
+          ctl->go2 = tc::mbar_wait_cluster(&ctl->xfull, step & 1, p.err, abort, tmo);
+          if (ctl->go2) x_done = step + 1;
+        }
+        epi_bar();
+        if (!ctl->go2) break;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          const float4 v = xbuf[(g * 4 + part) * BG + r];
+          acc[g][0] += v.x; acc[g][1] += v.y; acc[g][2] += v.z; acc[g][3] += v.w;
+        }
+        if (p.trace && blockIdx.x == 0 && threadIdx.x == 64) p.trace[step * 16 + 11] = globaltimer_ns();
+      }
       if (active) {
 #pragma unroll
         for (int j = 0; j < UPT; ++j) {
@@ -425,14 +482,30 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
         if (NG == 4 && p.c_n) p.c_n[((size_t)d * B + b) * H + ub + j] = c[j];
       }
     }
+    if (KS > 1) x_left = x_done < x_posted ? -x_done - 1 : x_done;  // < 0: phase x_done armed
   }
   tc::tc_fence_before();
   __syncthreads();
-  // no member leaves while a peer may still deliver loads or arrivals to it
-  if (cs > 1) tc::cluster_sync();
+  // no member leaves while a peer may still deliver loads, partial sums or
+  // arrivals to it
+  if (cs > 1 || KS > 1) tc::cluster_sync();
+  if (KS > 1 && threadIdx.x == 64) {
+    // After an early exit the peer may have sent one step more than this CTA
+    // consumed (never two: the peer's next step needs this CTA's arrival at
+    // the step barrier, made only after consuming).  Those stores land in this
+    // CTA's shared memory, so wait for them (bounded) before leaving.
+    const int done = x_left < 0 ? -x_left - 1 : x_left;
+    const uint32_t peer_sent =
+        tc::ld_cluster_u32(tc::mapa_shared(tc::smem_u32(&ctl->x_sent), (uint32_t)(1 - kr)));
+    if ((int)peer_sent > done) {
+      if (x_left >= 0) tc::mbar_arrive_expect_tx(&ctl->xfull, (uint32_t)geo.x_bytes);
+      volatile int never = 0;
+      tc::mbar_wait(&ctl->xfull, (uint32_t)done & 1u, nullptr, &never, 100000000ull);
+    }
+  }
   if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tbase, 64);
+    tc::tmem_dealloc(tbase, TCOLS);
   }
 }
 
@@ -470,7 +543,7 @@ bool tc_rec_packable(int cell, int H, int Hout, int P) {
   if (P > 0) return false;  // projection runs on the portable kernel
   if (H < 1 || Hout < 1) return false;
   const int nG = cell == CELL_LSTM ? 4 : 3;
-  return make_geo(nG, Hout).stages >= 2 && encode_fn() != nullptr;
+  return make_geo(nG, Hout, 1).stages >= 2 && encode_fn() != nullptr;
 }
 
 bool tc_rec_supported(int cell, int H, int Hout, int P, int nsm, int B, int D) {
@@ -496,63 +569,97 @@ void tc_pack_whh(int cell, int H, int Hout, const float *whh, std::vector<uint16
       }
 }
 
+namespace {
+
+template <int NG>
+const void *kernel_for(int ks) {
+  return ks == 2 ? (const void *)rec_tc_kernel<NG, 2> : (const void *)rec_tc_kernel<NG, 1>;
+}
+
+// Cooperative launch of `grid` CTAs in clusters of `cs`; false (nothing
+// launched) when that cluster grid cannot be resident at once.
+bool launch_clustered(const void *fn, int grid, int cs, size_t smem, void **args, cudaStream_t s,
+                      cudaError_t *err) {
+  *err = cudaSuccess;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(NT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  int max_clusters = 0;
+  cudaLaunchConfig_t q = cfg;
+  q.numAttrs = 1;  // occupancy query on the cluster shape
+  if (cudaOccupancyMaxActiveClusters(&max_clusters, fn, &q) != cudaSuccess ||
+      (long long)max_clusters * cs < grid) {
+    cudaGetLastError();
+    return false;
+  }
+  *err = cudaLaunchKernelExC(&cfg, fn, args);
+  return true;
+}
+
+}  // namespace
+
 cudaError_t launch_tc_recurrent(const TcRecParams &tp, int nsm, cudaStream_t s) {
   (void)nsm;
   RecParams p = tp.base;
   const int nG = p.nG;
-  const Geo geo = make_geo(nG, p.Hout);
-  p.NU = ceil_div(p.H, UNITS);
+  const int NU16 = ceil_div(p.H, UNITS);  // 16-unit tiles in the packed weights
   const int NBG = ceil_div(p.B, BG);
   Maps maps;
   if (!make_map(&maps.hx, p.hx, (long long)p.D * 2 * p.B, p.Hout, p.Kp, BG))
     return cudaErrorInvalidValue;
-  for (int d = 0; d < 2; ++d) {
-    const void *w = tp.Wtc[d < p.D ? d : 0];
-    if (!make_map(&maps.w[d], w, (long long)p.NU * geo.N, p.Hout, p.Kp, geo.N))
-      return cudaErrorInvalidValue;
-  }
-  const void *fn = nG == 4 ? (const void *)rec_tc_kernel<4> : (const void *)rec_tc_kernel<3>;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)geo.smem);
-  if (e != cudaSuccess) return e;
-  const int grid = p.D * NBG * p.NU;
-  // cluster size: requested, else the largest of 4, 2 dividing the unit groups
-  // Multicast was measured not to pay on GB300 for this kernel (the MMA
-  // phase is bound by the tensor pipe's rate on these small-N MMAs, not by
-  // L2 requests), so clusters are opt-in.
-  int cs = tp.cluster > 0 ? tp.cluster : 1;
-  while (cs > 1 && (p.NU % cs) != 0) cs /= 2;
-  if (cs > 1) {
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) { cudaGetLastError(); cs = 1; }
-  }
-  void *args[] = {&maps, &p};
-  if (cs > 1) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(NT);
-    cfg.dynamicSmemBytes = geo.smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeCooperative;
-    attr[1].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    int max_clusters = 0;
-    cudaLaunchConfig_t q = cfg;
-    q.numAttrs = 1;  // occupancy query on the cluster shape
-    if (cudaOccupancyMaxActiveClusters(&max_clusters, fn, &q) == cudaSuccess &&
-        max_clusters * cs >= grid) {
-      e = cudaLaunchKernelExC(&cfg, fn, args);
-      if (e == cudaSuccess) return cudaSuccess;
+
+  // K split over a CTA pair: requested, or automatic when each CTA keeps at
+  // least one K block, the plan fits shared memory and no multicast cluster
+  // was asked for
+  int ks = tp.ksplit;
+  const bool ks2_ok = make_geo(nG, p.Hout, 2).stages >= 2 && make_geo(nG, p.Hout, 2).nkb >= 2;
+  if (ks == 0) ks = (ks2_ok && tp.cluster <= 1) ? 2 : 1;
+  if (ks == 2 && !ks2_ok) ks = 1;
+
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    const Geo geo = make_geo(nG, p.Hout, ks);
+    p.NU = ks == 2 ? 2 * ceil_div(p.H, 2 * UNITS) : NU16;
+    for (int d = 0; d < 2; ++d) {
+      const void *w = tp.Wtc[d < p.D ? d : 0];
+      if (!make_map(&maps.w[d], w, (long long)NU16 * nG * UNITS, p.Hout, p.Kp, geo.N))
+        return cudaErrorInvalidValue;
     }
-    cudaGetLastError();  // fall back to the cluster-free launch
+    const void *fn = nG == 4 ? kernel_for<4>(ks) : kernel_for<3>(ks);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)geo.smem);
+    if (e != cudaSuccess) return e;
+    const int grid = p.D * NBG * p.NU;
+    void *args[] = {&maps, &p};
+    if (ks == 2) {
+      if (launch_clustered(fn, grid, 2, geo.smem, args, s, &e)) return e;
+      ks = 1;  // the pair grid cannot be co-resident: no split
+      continue;
+    }
+    // optional multicast cluster: the requested size, halved until it divides
+    // the unit groups.  Multicast was measured not to pay on GB300 for this
+    // kernel, so it is opt-in.
+    int cs = tp.cluster > 0 ? tp.cluster : 1;
+    while (cs > 1 && (p.NU % cs) != 0) cs /= 2;
+    if (cs > 1 && launch_clustered(fn, grid, cs, geo.smem, args, s, &e)) return e;
+    return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(NT), args, geo.smem, s);
   }
-  return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(NT), args, geo.smem, s);
+  return cudaErrorInvalidConfiguration;
 }
 
 }  // namespace rcu

@@ -243,11 +243,49 @@ def test_tensor_core_multicast_clusters(cluster):
     net.close()
 
 
-def test_barrier_timeout_on_tensor_core_path():
-    spec = wl.GRU_3L.scaled(layers=1, T=4, B=20, in_dim=16, hidden=64)
+KSPLIT = [
+    # two batch groups with a ragged tail; 13 sixteen-unit tiles (odd: the last
+    # pair has one tile of zero rows); H not a multiple of 16
+    wl.GRU_3L.scaled(layers=2, T=10, B=150, in_dim=40, hidden=200, h0_std=0.5),
+    wl.LSTM_T80.scaled(name="lstm_bf16", dtype="bf16", layers=1, T=8, B=129, in_dim=64,
+                       hidden=1000, h0_std=0.5, c0_std=0.5),
+    # varlen, both directions; odd number of K blocks (3) so the pair splits 2 + 1
+    wl.BILSTM_VAR.scaled(dtype="bf16", T=12, B=70, in_dim=24, hidden=150, varlen=(1, 12)),
+    wl.GRU_3L.scaled(layers=1, T=6, B=256, in_dim=32, hidden=1024),
+]
+
+
+@pytest.mark.parametrize("spec", KSPLIT, ids=lambda s: f"{s.name}-T{s.T}-B{s.B}-H{s.hidden}")
+@pytest.mark.parametrize("ksplit", [1, 2])
+def test_tensor_core_k_split(spec, ksplit):
+    """h W_hh^T with K kept whole (1) or split over a CTA pair (2) whose
+    partial sums are exchanged through distributed shared memory."""
+    inp = wl.make_rnn_inputs(spec, seed=17)
+    dev = torch.device("cuda")
+    net = binding.RNN.from_spec(spec)
+    net.set_attr(binding.RCU_ATTR_FORCE_PATH, 2)
+    net.set_attr(binding.RCU_ATTR_TC_KSPLIT, ksplit)
+    net.set_attr(binding.RCU_ATTR_PROFILE, 1)
+    net.set_weights(inp["weights"])
+    lengths = inp["lengths"].to(dev) if inp["lengths"] is not None else None
+    h0 = inp["h0"].to(dev) if inp["h0"] is not None else None
+    c0 = inp["c0"].to(dev) if inp["c0"] is not None else None
+    y, hn, cn = net.forward(inp["x"].to(dev), lengths=lengths, h0=h0, c0=c0)
+    assert net.status() == 0
+    torch.cuda.synchronize()
+    assert "recurrent_tc" in net.profile()
+    got = (y.cpu().numpy(), hn.cpu().numpy(), None if cn is None else cn.cpu().numpy())
+    compare(spec, got, run_oracle(spec, inp))
+    net.close()
+
+
+@pytest.mark.parametrize("ksplit", [1, 2])
+def test_barrier_timeout_on_tensor_core_path(ksplit):
+    spec = wl.GRU_3L.scaled(layers=1, T=4, B=20, in_dim=16, hidden=128)
     inp = wl.make_rnn_inputs(spec, seed=14)
     dev = torch.device("cuda")
     net = binding.RNN.from_spec(spec)
+    net.set_attr(binding.RCU_ATTR_TC_KSPLIT, ksplit)
     net.set_weights(inp["weights"])
     net.set_attr(binding.RCU_ATTR_BARRIER_TIMEOUT_NS, 50_000_000)
     net.set_attr(binding.RCU_ATTR_TEST_DROP_ARRIVAL, 1)
