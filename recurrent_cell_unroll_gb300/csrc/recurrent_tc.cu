@@ -135,7 +135,15 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   volatile int *abort = &ctl->abort;
   const uint64_t tmo = p.timeout_ns;
-  unsigned *ctr = p.ctr + d * NBG + bg;
+  // Step barrier counters, one per K share of (d, bg): a CTA waits only for
+  // the CTAs that produce the h units of its own K blocks and arrives on the
+  // counter of the share its units fall in.  CTA c of (d, bg) finalises units
+  // [16c, 16c+16), and a K share boundary (nkbm*64) is a multiple of 16.
+  const int kbound = geo.nkbm * BK;
+  unsigned *ctr = p.ctr + (size_t)(d * NBG + bg) * KS + kr;
+  unsigned *ctr_arrive = p.ctr + (size_t)(d * NBG + bg) * KS + (KS > 1 && u0 >= kbound ? 1 : 0);
+  const int n_lo = KS > 1 ? min(NU, kbound / UNITS) : NU;  // CTAs arriving on share 0
+  const unsigned n_wait = (unsigned)(kr == 0 ? n_lo : NU - n_lo);
   // steps this batch group runs: the longest row of the group (rows sorted by length)
   const int Tg = row0 < B ? p.meta.lens_sorted[row0] : 0;
   // without a K split, an optional cluster of CTAs sharing (d, bg): each
@@ -185,7 +193,7 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
       uint32_t pend_phase[MAX_STAGES];
       for (int step = 0; step < Tg; ++step) {
         // wait until every CTA of (d, bg) has published h_{step-1}
-        const unsigned target = (unsigned)(NU * (step + 1));
+        const unsigned target = n_wait * (unsigned)(step + 1);
         if (ld_acquire_gpu(ctr) < target) {
           const uint64_t deadline = globaltimer_ns() + tmo;
           uint32_t spins = 0;
@@ -340,7 +348,7 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
     fence_proxy_async_global();
     epi_bar();
     if (threadIdx.x == 64) {
-      red_release_gpu_add(ctr, (p.drop_arrival && blockIdx.x == 0) ? 0u : 1u);
+      red_release_gpu_add(ctr_arrive, (p.drop_arrival && blockIdx.x == 0) ? 0u : 1u);
     }
     for (int step = 0; step < Tg; ++step) {
       const bool active = row_ok && step < len;
@@ -452,7 +460,7 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
       epi_bar();
       if (threadIdx.x == 64) {
         if (p.trace && blockIdx.x == 0) p.trace[step * 16 + 7] = globaltimer_ns();
-        red_release_gpu_add(ctr, 1u);  // release: orders the epilogue's h_t stores
+        red_release_gpu_add(ctr_arrive, 1u);  // release: orders the epilogue's h_t stores
         if (p.trace && blockIdx.x == 0) p.trace[step * 16 + 4] = globaltimer_ns();
       }
       // outputs leave the critical path: written after h_t is published
@@ -552,7 +560,7 @@ bool tc_rec_supported(int cell, int H, int Hout, int P, int nsm, int B, int D) {
   return ctas <= nsm;
 }
 
-int tc_rec_counters(int B, int D) { return D * ceil_div(B, BG); }
+int tc_rec_counters(int B, int D) { return 2 * D * ceil_div(B, BG); }
 
 void tc_pack_whh(int cell, int H, int Hout, const float *whh, std::vector<uint16_t> &out,
                  uint16_t (*to_bf16)(float)) {
