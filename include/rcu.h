@@ -72,7 +72,9 @@ typedef struct rcu_rssm_s *rcu_rssm_t;
 #define RCU_ATTR_TEST_DROP_ARRIVAL 2  /* testing only: 1 = one CTA never arrives at the
                                          first step barrier, so the wait must time out */
 #define RCU_ATTR_FORCE_PATH 3         /* 0 = automatic, 1 = portable SIMT kernels only,
-                                         2 = tensor-core (tcgen05) kernels where supported */
+                                         2 = tensor-core (tcgen05) kernels where supported,
+                                         3 = cluster-resident recurrent kernel where W_hh
+                                         fits one thread-block cluster (else SIMT) */
 #define RCU_ATTR_TRACE 5              /* 1 = record per-step timestamps (rnn_get_trace) */
 #define RCU_ATTR_TC_CLUSTER 6         /* tensor-core recurrent kernel: CTAs per thread-block
                                          cluster that share each h tile by TMA multicast

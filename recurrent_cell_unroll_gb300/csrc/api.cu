@@ -97,6 +97,7 @@ struct DevBuf {
 struct LayerDirW {
   DevBuf whh, whr, bhn;  // SIMT-packed recurrent weights, projection, GRU b_hn
   DevBuf tc_whh;         // tensor-core packed recurrent weights (bf16 path)
+  DevBuf cl_whh;         // cluster-resident layout [H*nG][Kc] (small W_hh, no projection)
   // bf16 LSTMP tensor-core path: packed W_hh W_hr, fp32 copy of the rounded
   // W_hh (initial-state term) and bf16 W_hr [P][round_up(H, 8)] (projection GEMM)
   DevBuf fold_w, whh_f32, whr_bf;
@@ -279,7 +280,7 @@ extern "C" int rnn_set_attr(rcu_rnn_t h, int attr, int64_t value) {
       h->trace = value != 0;
       return RCU_OK;
     case RCU_ATTR_FORCE_PATH:
-      if (value < 0 || value > 2) return fail(RCU_ERR_INVALID, "force_path must be 0, 1 or 2");
+      if (value < 0 || value > 3) return fail(RCU_ERR_INVALID, "force_path must be 0, 1, 2 or 3");
       h->force_path = (int)value;
       return RCU_OK;
     default: return fail(RCU_ERR_INVALID, "rnn_set_attr: unknown attribute %d", attr);
@@ -375,6 +376,15 @@ extern "C" int rnn_set_weights(rcu_rnn_t h, int layer, int dir, const float *W_i
     std::vector<uint16_t> packed;
     tc_pack_whh(h->cell, H, Hout, whh.data(), packed, f2bf);
     CU(lw.tc_whh.upload(packed.data(), packed.size() * 2));
+  }
+  // --- cluster-resident layout (LSTM/GRU without projection whose W_hh fits
+  //     one thread-block cluster's shared memory)
+  if (cluster_rec_packable(h->cell, H, Hout, P, bf)) {
+    std::vector<float> cw;
+    cluster_pack_whh(h->cell, H, Hout, whh.data(), cw);
+    std::vector<unsigned char> buf(cw.size() * es);
+    for (size_t i = 0; i < cw.size(); ++i) put(buf, i, cw[i]);
+    CU(lw.cl_whh.upload(buf.data(), buf.size()));
   }
   // --- LSTMP on the tensor cores: recurrent weight W_hh W_hr over m (from the
   //     bf16-rounded factors, product accumulated in fp32, rounded to bf16)
@@ -641,10 +651,17 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
     }
 
     bool rec_done = false;
-    const bool tc_rec = bf && h->force_path != 1 &&
+    const bool tc_rec = bf && (h->force_path == 0 || h->force_path == 2) &&
                         tc_rec_supported(h->cell, H, Hout, h->P, h->nsm, B, D) &&
                         h->lw[(size_t)l * D].tc_whh.p;
-    h->begin(tc_rec ? "recurrent_tc" : "recurrent_simt", s);
+    // small problems: the cluster-resident kernel (automatic for slices of at
+    // most 16 rows per cluster)
+    ClusterRecPlan cp{};
+    const bool cl_rec = !tc_rec && (h->force_path == 0 || h->force_path == 3) &&
+                        h->lw[(size_t)l * D].cl_whh.p &&
+                        plan_recurrent_cluster(&cp, h->cell, H, Hout, T, B, D, bf,
+                                               h->force_path == 3 ? (1 << 30) : 16);
+    h->begin(tc_rec ? "recurrent_tc" : cl_rec ? "recurrent_cluster" : "recurrent_simt", s);
     if (tc_rec) {
       TcRecParams tp;
       tp.base = p;
@@ -655,6 +672,12 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
       if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "tc recurrent: %s", cudaGetErrorString(e));
       rec_done = true;
       h->used_tc_rec = true;
+    } else if (cl_rec) {
+      cudaError_t e = launch_recurrent_cluster(p, cp, h->lw[(size_t)l * D].cl_whh.p,
+                                               h->lw[(size_t)l * D + (D - 1)].cl_whh.p, bf, s);
+      if (e != cudaSuccess)
+        return fail(RCU_ERR_CUDA, "cluster recurrent kernel: %s", cudaGetErrorString(e));
+      rec_done = true;
     }
     if (!rec_done) {
       // the batch chunk is shrunk until the shared-memory plan fits

@@ -6,6 +6,11 @@
 //
 // Tile 128x128x16, 256 threads, 8x8 outputs per thread, double-buffered
 // shared memory.  Operands may be fp32 or bf16; accumulation is fp32.
+// When the output tiles are too few to fill the GPU (short sequences, small
+// batches) K is split over a thread-block cluster of S CTAs along z: each
+// parks its partial tile in shared memory and rank z sums rows [z*128/S,
+// (z+1)*128/S) of all S partials over distributed shared memory, in rank
+// order, so the result does not depend on timing.
 #include "common.cuh"
 #include "internal.h"
 
@@ -24,10 +29,13 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const XT *__restrict__ X,
                                                        const float *__restrict__ bias,
                                                        float *__restrict__ G, int ldg, int M,
                                                        const int32_t *__restrict__ M_dev, int N,
-                                                       int K) {
+                                                       int K, int kchunk) {
   if (M_dev) M = *M_dev;
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  // every CTA of a K-split cluster shares (m0, n0), so they leave together
   if (m0 >= M) return;
+  const int S = gridDim.z, z = blockIdx.z;
+  const int kbeg = z * kchunk, kend = min(K, kbeg + kchunk);
   __shared__ __align__(16) float As[2][BK][BM + 4];
   __shared__ __align__(16) float Bs[2][BK][BN + 4];
   const int tid = threadIdx.x;
@@ -48,8 +56,8 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const XT *__restrict__ X,
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       const int k = k0 + lk + q;
-      ra[q] = (am < M && k < K) ? ldf(X + (size_t)am * ldx + k) : 0.f;
-      rb[q] = (bn < N && k < K) ? ldf(W + (size_t)bn * ldw + k) : 0.f;
+      ra[q] = (am < M && k < kend) ? ldf(X + (size_t)am * ldx + k) : 0.f;
+      rb[q] = (bn < N && k < kend) ? ldf(W + (size_t)bn * ldw + k) : 0.f;
     }
   };
   auto store_smem = [&](int buf) {
@@ -60,13 +68,13 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const XT *__restrict__ X,
     }
   };
 
-  const int nk = ceil_div(K, BK);
-  load_regs(0);
+  const int nk = kend > kbeg ? ceil_div(kend - kbeg, BK) : 0;
+  load_regs(kbeg);
   store_smem(0);
   __syncthreads();
   for (int kt = 0; kt < nk; ++kt) {
     const int buf = kt & 1;
-    if (kt + 1 < nk) load_regs((kt + 1) * BK);
+    if (kt + 1 < nk) load_regs(kbeg + (kt + 1) * BK);
 #pragma unroll
     for (int kk = 0; kk < BK; ++kk) {
       float a[8], b[8];
@@ -87,6 +95,49 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const XT *__restrict__ X,
     __syncthreads();
   }
 
+  if (S > 1) {
+    extern __shared__ __align__(16) float Ps[];  // [BM][BN + 4] partial tile
+    constexpr int LDP = BN + 4;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4);
+      *reinterpret_cast<float4 *>(&Ps[r * LDP + tx * 4]) =
+          make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      *reinterpret_cast<float4 *>(&Ps[r * LDP + 64 + tx * 4]) =
+          make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+    }
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                     "memory");
+    const int rows = BM / S;
+    for (int e = tid; e < rows * (BN / 4); e += NT) {
+      const int r = z * rows + e / (BN / 4), c = (e % (BN / 4)) * 4;
+      const uint32_t local = (uint32_t)__cvta_generic_to_shared(&Ps[r * LDP + c]);
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int q = 0; q < S; ++q) {
+        uint32_t ra_;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra_) : "r"(local), "r"(q));
+        float4 v;
+        asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                     : "r"(ra_)
+                     : "memory");
+        a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+      }
+      const int m = m0 + r;
+      if (m < M) {
+        const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int n = n0 + c + j;
+          if (n < N) G[(size_t)m * ldg + n] = av[j] + (bias ? bias[n] : 0.f);
+        }
+      }
+    }
+    // no CTA leaves while a peer may still read its partial tile
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                     "memory");
+    return;
+  }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int m = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
@@ -107,7 +158,37 @@ cudaError_t launch_gemm_simt(const XT *X, int ldx, const WT *W, int ldw, const f
                              cudaStream_t s) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   dim3 grid(ceil_div(N, BN), ceil_div(M, BM));
-  gemm_simt_kernel<XT, WT><<<grid, NT, 0, s>>>(X, ldx, W, ldw, bias, G, ldg, M, M_dev, N, K);
+  const int tiles = (int)(grid.x * grid.y);
+  int dev = 0, nsm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  // K split: powers of two up to 8 while the grid stays under two CTAs per SM
+  // and every slice keeps at least two K tiles
+  int S = 1;
+  while (S < 8 && tiles * S * 2 <= 2 * nsm && K >= 2 * BK * (S * 2)) S *= 2;
+  const void *fn = (const void *)gemm_simt_kernel<XT, WT>;
+  if (S > 1) {
+    const int kchunk = round_up(ceil_div(K, S), BK);
+    const size_t smem = (size_t)BM * (BN + 4) * 4;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid.x, grid.y, S);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = 1;
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = S;
+    cfg.attrs = a;
+    cfg.numAttrs = 1;
+    int kc = kchunk;
+    void *args[] = {&X, &ldx, &W, &ldw, &bias, &G, &ldg, &M, &M_dev, &N, &K, &kc};
+    return cudaLaunchKernelExC(&cfg, fn, args);
+  }
+  gemm_simt_kernel<XT, WT><<<grid, NT, 0, s>>>(X, ldx, W, ldw, bias, G, ldg, M, M_dev, N, K, K);
   return cudaGetLastError();
 }
 

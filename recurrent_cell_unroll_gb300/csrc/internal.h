@@ -1,6 +1,8 @@
 // Internal launchers shared by the host API (api.cu) and the kernel files.
 #pragma once
 
+#include <vector>
+
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -72,6 +74,22 @@ cudaError_t launch_recurrent_simt(const RecParams &p, bool wbf16, int nsm, cudaS
 size_t recurrent_simt_smem(const RecParams &p, bool wbf16);
 // choose the batch chunk p.CB so that the shared-memory plan fits; false if none does
 bool plan_recurrent_simt(RecParams &p, bool wbf16);
+
+// ---- recurrent_cluster.cu: cluster-resident kernel for a W_hh that fits one
+// thread-block cluster (LSTM / GRU without projection)
+struct ClusterRecPlan {
+  int cs, U, Kc, Bc, NCL;  // cluster size, units per CTA, padded K, rows per cluster, clusters per direction
+  size_t smem;
+};
+int cluster_rec_kc(int Hout);
+bool cluster_rec_packable(int cell, int H, int Hout, int P, bool wbf16);
+// rows u*nG + g (gate g of unit u), Kc = cluster_rec_kc(Hout) columns, zero padded
+void cluster_pack_whh(int cell, int H, int Hout, const float *whh, std::vector<float> &out);
+// false when no cluster plan fits, or the batch slice would exceed max_rows
+bool plan_recurrent_cluster(ClusterRecPlan *cp, int cell, int H, int Hout, int T, int B, int D,
+                            bool wbf16, int max_rows);
+cudaError_t launch_recurrent_cluster(const RecParams &p, const ClusterRecPlan &cp,
+                                     const void *W0, const void *W1, bool wbf16, cudaStream_t s);
 
 // ---- lstmp_fold.cu -------------------------------------------------------------
 // G rows of each sequence's first step (direction d) += W_hh h0 (W_hh fp32 [4H][P]).

@@ -1,0 +1,360 @@
+// Cluster-resident recurrent kernel (LSTM / GRU without projection) for
+// problems whose W_hh fits the shared memory of one thread-block cluster.
+//
+// A cluster of cs CTAs (16 where the GPU allows it, else 8) keeps one copy
+// of a direction's W_hh: CTA `rank` holds the rows of units
+// [rank*U, rank*U + U), all gates, in shared memory for the whole sequence.
+// Clusters take disjoint slices of Bc sorted batch rows, so they never wait
+// for one another; a step needs only the cluster's own hardware barrier.
+// Per step each CTA
+//   1. computes its rows of h_{t-1} W_hh^T for the active rows of its slice
+//      (the "recurrent hidden-hidden dense" of "[TOPI] TE implementation of
+//      LSTM using scan", apache/tvm PR 11531): 8 lanes per output row, each
+//      taking every 8th 16-byte K chunk, then a 3-level shuffle reduction;
+//   2. adds the input projection G (prefetched during the previous step),
+//      applies the gates and the cell update (c and h stay in registers, one
+//      (row, unit) pair per thread);
+//   3. stores h_t into the h buffer of every CTA of the cluster (distributed
+//      shared memory, double-buffered by step parity) and crosses the step
+//      with barrier.cluster (release/acquire), writing y after its arrival.
+// Rows whose length is exhausted leave the active prefix of the sorted batch
+// ("RNN Op Changes", apache/mxnet issue 9543); the backward direction runs
+// row s at time len_s - 1 - step.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace rcu {
+
+namespace {
+
+constexpr int NT = 512;
+constexpr int NW = NT / 32;
+constexpr int KC_MAX = 1024;  // padded K (multiple of 128)
+constexpr int SMEM_LIMIT = 227 * 1024;
+
+constexpr int SOFF_MAX = 4096;  // step offsets staged in shared memory up to this T
+
+struct CSmem {
+  size_t w, h, pre, lens, soff, total;
+};
+__host__ __device__ inline CSmem cl_smem(int R, int Kc, int Bc, size_t es, int T) {
+  CSmem L;
+  size_t o = 0;
+  L.w = o;
+  o += (size_t)R * Kc * es;
+  o = round_up_sz(o, 16);
+  L.h = o;
+  o += (size_t)2 * Bc * Kc * 4;
+  L.pre = o;
+  o += (size_t)Bc * R * 4;
+  L.lens = o;
+  o += (size_t)Bc * 4;
+  L.soff = o;
+  if (T <= SOFF_MAX) o += (size_t)T * 4;
+  L.total = o;
+  return L;
+}
+
+__device__ __forceinline__ uint32_t cl_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cl_size() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cl_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cl_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cl_map(const void *p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(r)
+               : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cl(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ float4 wload(const float *p) {
+  return *reinterpret_cast<const float4 *>(p);
+}
+__device__ __forceinline__ float4 wload(const __nv_bfloat16 *p) {
+  const uint2 v = *reinterpret_cast<const uint2 *>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&v.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+template <typename WT, int NG>
+__global__ void __launch_bounds__(NT, 1)
+    rec_cluster_kernel(const RecParams p, const void *W0, const void *W1, int U, int Kc, int Bc,
+                       int NCL) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const uint32_t cs = cl_size(), rank = cl_rank();
+  const int ci = blockIdx.x / cs;
+  const int d = ci / NCL, slice = ci % NCL;
+  const int B = p.B, H = p.H, Hout = p.Hout;
+  const int r0 = slice * Bc;                   // first sorted row of the slice
+  const int nrow = max(0, min(Bc, B - r0));    // rows of the slice
+  const int u0 = (int)rank * U;
+  const int nu = max(0, min(U, H - u0));       // valid units of this CTA
+  const int R = NG * U;                        // local row j*NG + g = gate g of unit u0 + j
+  const int KQ = Kc / 32;  // 16-byte K chunks per lane of an 8-lane group
+  const CSmem L = cl_smem(R, Kc, Bc, sizeof(WT), p.T);
+  WT *Ws = reinterpret_cast<WT *>(smem + L.w);
+  float *hb = reinterpret_cast<float *>(smem + L.h);     // [2][Bc][Kc]
+  float *pre = reinterpret_cast<float *>(smem + L.pre);  // [Bc][R]
+  int *slens = reinterpret_cast<int *>(smem + L.lens);   // [Bc] lengths of the slice's rows
+  int *ssoff = reinterpret_cast<int *>(smem + L.soff);   // [T] packed row offset of each step
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int grp = lane / 8, gl = lane % 8;
+
+  {  // resident weights (16-byte copies; rows past the last unit are zero)
+    const size_t n16 = (size_t)R * Kc * sizeof(WT) / 16;
+    const size_t v16 = (size_t)nu * NG * Kc * sizeof(WT) / 16;
+    const uint4 *src = reinterpret_cast<const uint4 *>(d ? W1 : W0) +
+                       (size_t)u0 * NG * Kc * sizeof(WT) / 16;
+    uint4 *dst = reinterpret_cast<uint4 *>(Ws);
+    for (size_t i = threadIdx.x; i < n16; i += NT)
+      dst[i] = i < v16 ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < 2 * Bc * Kc; i += NT) hb[i] = 0.f;
+  }
+  const int32_t *sidx = p.meta.sorted_idx;
+  const int32_t *lens = p.meta.lens_sorted;
+  // per-step metadata in shared memory, off the step's critical path
+  for (int i = threadIdx.x; i < nrow; i += NT) slens[i] = lens[r0 + i];
+  const int32_t *soff = p.meta.step_off;
+  if (p.T <= SOFF_MAX) {
+    for (int i = threadIdx.x; i < p.T; i += NT) ssoff[i] = soff[i];
+    soff = ssoff;
+  }
+  const int Tcl = nrow > 0 ? lens[r0] : 0;  // steps of the slice (rows sorted by length)
+  const int ldo = p.D * Hout;
+
+  // this thread's (row, unit) pair
+  const int bq = threadIdx.x / U, jq = threadIdx.x % U;
+  const bool own = bq < nrow && jq < nu;
+  const int s = r0 + bq, u = u0 + jq;
+  int len = 0, borig = 0;
+  float c = 0.f, hv = 0.f, bn = 0.f;
+  if (own) {
+    len = lens[s];
+    borig = sidx[s];
+    hv = p.h0 ? p.h0[((size_t)d * B + borig) * Hout + u] : 0.f;
+    if (NG == 4 && p.c0) c = p.c0[((size_t)d * B + borig) * H + u];
+    if (NG == 3 && p.bhn[d]) bn = p.bhn[d][u];
+  }
+  float gx[NG];
+#pragma unroll
+  for (int q = 0; q < NG; ++q) gx[q] = 0.f;
+  auto prefetch = [&](int step) {
+    if (!own || step >= len) return;
+    const int tt = d == 0 ? step : len - 1 - step;
+    const float *g = p.G + ((size_t)soff[tt] + s) * p.ldG + (size_t)d * NG * H + u;
+#pragma unroll
+    for (int q = 0; q < NG; ++q) gx[q] = __ldg(g + (size_t)q * H);
+  };
+  // every CTA's h buffers are zeroed (and the metadata staged) before any
+  // peer writes into them
+  __syncthreads();
+  cl_arrive();
+  cl_wait();
+  if (own) {
+    for (uint32_t q = 0; q < cs; ++q) st_cl(cl_map(hb + (size_t)bq * Kc + u, q), hv);
+  }
+  prefetch(0);
+  cl_arrive();
+  cl_wait();
+
+  int nact = nrow;  // active rows: the prefix of the slice with length > step
+  for (int step = 0; step < Tcl; ++step) {
+    const bool tr = p.trace && blockIdx.x == 0 && threadIdx.x == 0;
+    if (tr) p.trace[step * 16 + 0] = globaltimer_ns();
+    while (nact > 0 && slens[nact - 1] <= step) --nact;
+    const float *hcur = hb + (size_t)(step & 1) * Bc * Kc;
+    float *hnxt = hb + (size_t)((step & 1) ^ 1) * Bc * Kc;
+    // ---- h_{t-1} W_hh^T: a group of 8 lanes per output row (4 rows per warp
+    //      pass); lane l of a group takes the 16-byte K chunks l, l+8, ...
+    for (int b = 0; b < nact; ++b) {
+      const float *hrow = hcur + (size_t)b * Kc + 4 * gl;
+      for (int rw = warp * 4; rw < R; rw += NW * 4) {
+        const int r = rw + grp;
+        float a = 0.f;
+        if (r < R) {
+          const WT *wr = Ws + (size_t)r * Kc + 4 * gl;
+#pragma unroll 4
+          for (int m = 0; m < KQ; ++m) {
+            const float4 w = wload(wr + 32 * m);
+            const float4 x = *reinterpret_cast<const float4 *>(hrow + 32 * m);
+            a = fmaf(w.x, x.x, a);
+            a = fmaf(w.y, x.y, a);
+            a = fmaf(w.z, x.z, a);
+            a = fmaf(w.w, x.w, a);
+          }
+        }
+        a += __shfl_xor_sync(0xffffffffu, a, 4);
+        a += __shfl_xor_sync(0xffffffffu, a, 2);
+        a += __shfl_xor_sync(0xffffffffu, a, 1);
+        if (gl == 0 && r < R) pre[(size_t)b * R + r] = a;
+      }
+    }
+    __syncthreads();
+    if (tr) p.trace[step * 16 + 3] = globaltimer_ns();
+    // ---- gates and cell update; h_t into every CTA's next-step buffer
+    const bool act = own && bq < nact;
+    if (act) {
+      const float *pr = pre + (size_t)bq * R + (size_t)jq * NG;
+      if (NG == 4) {
+        const float ig = sigmoid_f(pr[0] + gx[0]);
+        const float fg = sigmoid_f(pr[1] + gx[1]);
+        const float gg = tanh_f(pr[2] + gx[2]);
+        const float og = sigmoid_f(pr[3] + gx[3]);
+        c = fg * c + ig * gg;
+        hv = og * tanh_f(c);
+      } else {
+        const float rg = sigmoid_f(gx[0] + pr[0]);
+        const float zg = sigmoid_f(gx[1] + pr[1]);
+        const float ng = tanh_f(gx[2] + rg * (pr[NG - 1] + bn));
+        hv = (1.f - zg) * ng + zg * hv;
+      }
+      if (tr) p.trace[step * 16 + 4] = globaltimer_ns();
+      for (uint32_t q = 0; q < cs; ++q) st_cl(cl_map(hnxt + (size_t)bq * Kc + u, q), hv);
+    }
+    if (tr) p.trace[step * 16 + 1] = globaltimer_ns();
+    cl_arrive();
+    // outputs and the next step's G loads leave the critical path
+    if (act) {
+      const int tt = d == 0 ? step : len - 1 - step;
+      if (p.y) p.y[((size_t)tt * B + borig) * ldo + (size_t)d * Hout + u] = hv;
+      if (p.ymid)
+        reinterpret_cast<WT *>(p.ymid)[((size_t)soff[tt] + s) * ldo + (size_t)d * Hout + u] =
+            Op<WT>::from_f(hv);
+    }
+    prefetch(step + 1);
+    cl_wait();
+    if (tr) p.trace[step * 16 + 2] = globaltimer_ns();
+  }
+  if (own) {
+    if (p.h_n) p.h_n[((size_t)d * B + borig) * Hout + u] = hv;
+    if (NG == 4 && p.c_n) p.c_n[((size_t)d * B + borig) * H + u] = c;
+  }
+}
+
+template <typename WT>
+const void *cluster_kernel(int nG) {
+  return nG == 4 ? (const void *)rec_cluster_kernel<WT, 4> : (const void *)rec_cluster_kernel<WT, 3>;
+}
+
+}  // namespace
+
+int cluster_rec_kc(int Hout) { return round_up(Hout, 128); }
+
+bool cluster_rec_packable(int cell, int H, int Hout, int P, bool wbf16) {
+  if (P > 0 || H < 1 || Hout < 1) return false;
+  const int Kc = cluster_rec_kc(Hout);
+  if (Kc > KC_MAX) return false;
+  const int nG = cell == CELL_LSTM ? 4 : 3;
+  const int U = ceil_div(H, 16);  // the largest cluster
+  return cl_smem(nG * U, Kc, 1, wbf16 ? 2 : 4, 1).total <= (size_t)SMEM_LIMIT;
+}
+
+void cluster_pack_whh(int cell, int H, int Hout, const float *whh, std::vector<float> &out) {
+  const int nG = cell == CELL_LSTM ? 4 : 3, Kc = cluster_rec_kc(Hout);
+  out.assign((size_t)H * nG * Kc, 0.f);
+  for (int u = 0; u < H; ++u)
+    for (int g = 0; g < nG; ++g)
+      for (int k = 0; k < Hout; ++k)
+        out[((size_t)u * nG + g) * Kc + k] = whh[(size_t)(g * H + u) * Hout + k];
+}
+
+bool plan_recurrent_cluster(ClusterRecPlan *cp, int cell, int H, int Hout, int T, int B, int D,
+                            bool wbf16, int max_rows) {
+  const int nG = cell == CELL_LSTM ? 4 : 3, Kc = cluster_rec_kc(Hout);
+  const size_t es = wbf16 ? 2 : 4;
+  const void *fn = wbf16 ? cluster_kernel<__nv_bfloat16>(nG) : cluster_kernel<float>(nG);
+  for (int cs : {16, 8}) {
+    const int U = ceil_div(H, cs);
+    if (cs > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                      cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    // the batch slice: as many co-resident clusters as the GPU holds, then
+    // the smallest slice that covers B
+    const size_t smem1 = cl_smem(nG * U, Kc, 1, es, T).total;
+    if (smem1 > (size_t)SMEM_LIMIT) continue;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      continue;
+    }
+    cudaLaunchConfig_t q = {};
+    q.gridDim = dim3(cs);
+    q.blockDim = dim3(NT);
+    q.dynamicSmemBytes = smem1;
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = cs;
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = 1;
+    q.attrs = a;
+    q.numAttrs = 1;
+    int maxcl = 0;
+    if (cudaOccupancyMaxActiveClusters(&maxcl, fn, &q) != cudaSuccess || maxcl < 1) {
+      cudaGetLastError();
+      continue;
+    }
+    const int per_dir = std::max(1, maxcl / D);
+    const int Bc = ceil_div(std::max(B, 1), per_dir);
+    if (Bc > max_rows || Bc * U > NT) continue;
+    const size_t smem = cl_smem(nG * U, Kc, Bc, es, T).total;
+    if (smem > (size_t)SMEM_LIMIT) continue;
+    cp->cs = cs;
+    cp->U = U;
+    cp->Kc = Kc;
+    cp->Bc = Bc;
+    cp->NCL = ceil_div(std::max(B, 1), Bc);
+    cp->smem = smem;
+    return true;
+  }
+  return false;
+}
+
+cudaError_t launch_recurrent_cluster(const RecParams &p, const ClusterRecPlan &cp,
+                                     const void *W0, const void *W1, bool wbf16, cudaStream_t s) {
+  const void *fn = wbf16 ? cluster_kernel<__nv_bfloat16>(p.nG) : cluster_kernel<float>(p.nG);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)cp.smem);
+  if (e != cudaSuccess) return e;
+  if (cp.cs > 8) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.D * cp.NCL * cp.cs);
+  cfg.blockDim = dim3(NT);
+  cfg.dynamicSmemBytes = cp.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute a[1];
+  a[0].id = cudaLaunchAttributeClusterDimension;
+  a[0].val.clusterDim.x = cp.cs;
+  a[0].val.clusterDim.y = 1;
+  a[0].val.clusterDim.z = 1;
+  cfg.attrs = a;
+  cfg.numAttrs = 1;
+  RecParams pc = p;
+  int U = cp.U, Kc = cp.Kc, Bc = cp.Bc, NCL = cp.NCL;
+  void *args[] = {&pc, const_cast<void **>(&W0), const_cast<void **>(&W1), &U, &Kc, &Bc, &NCL};
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+}  // namespace rcu

@@ -35,6 +35,7 @@ namespace {
 constexpr int NT = 512;
 constexpr int KS_MAX = 8;
 constexpr int STATE_SMEM_MAX = 8192;  // B*U entries kept in shared memory (per array)
+constexpr int BSZ_SMEM_MAX = 4096;    // batch_sizes staged in shared memory up to this T
 
 __device__ __forceinline__ void load4(const float *p, float (&w)[4]) {
   const float4 v = *reinterpret_cast<const float4 *>(p);
@@ -145,7 +146,7 @@ __device__ __forceinline__ float red_sum(const float *red, int ks, int CB, int R
 }
 
 struct Smem {
-  size_t ws, wr, hs, red, st, total;
+  size_t ws, wr, hs, red, st, bsz, total;
 };
 __host__ __device__ inline Smem smem_layout(const RecParams &p, size_t wsz) {
   const bool proj = p.proj > 0;
@@ -169,6 +170,8 @@ __host__ __device__ inline Smem smem_layout(const RecParams &p, size_t wsz) {
   o += red * 4;
   L.st = o;
   if (!proj && (size_t)p.B * p.U <= STATE_SMEM_MAX) o += (size_t)2 * p.B * p.U * 4;
+  L.bsz = o;
+  if (p.T <= BSZ_SMEM_MAX) o += (size_t)p.T * 4;
   L.total = o;
   return L;
 }
@@ -229,6 +232,12 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
   const int32_t *sidx = p.meta.sorted_idx;
   const int32_t *lens = p.meta.lens_sorted;
   const int32_t *bsz = p.meta.batch_sizes;
+  if (p.T <= BSZ_SMEM_MAX) {  // the step's active-row count, off the critical path
+    int *sb = reinterpret_cast<int *>(smem + L.bsz);
+    for (int i = threadIdx.x; i < p.T; i += NT) sb[i] = bsz[i];
+    bsz = sb;
+    __syncthreads();
+  }
   const int32_t *soff = p.meta.step_off;
   const int ldo = p.D * Hout;
 

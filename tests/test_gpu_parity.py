@@ -279,6 +279,43 @@ def test_tensor_core_k_split(spec, ksplit):
     net.close()
 
 
+CLUSTER = [
+    wl.LSTM_T80,  # one row: one cluster of 16 CTAs
+    wl.LSTM_T80.scaled(T=9, B=7, in_dim=33, hidden=70, c0_std=0.5, h0_std=0.5),
+    wl.LSTM_T80.scaled(name="lstm2l", layers=2, T=11, B=37, in_dim=20, hidden=45),
+    wl.GRU_3L.scaled(dtype="f32", layers=2, bidir=True, T=9, B=5, in_dim=16, hidden=24,
+                     varlen=(1, 9)),
+    wl.BILSTM_VAR.scaled(T=21, B=33, in_dim=24, hidden=300, varlen=(1, 21), h0_std=0.3,
+                         c0_std=0.3),
+    wl.GRU_3L.scaled(dtype="f32", layers=1, T=12, B=37, in_dim=40, hidden=200),
+    wl.LSTM_T80.scaled(name="lstm_bf16", dtype="bf16", layers=2, T=12, B=150, in_dim=40,
+                       hidden=70, h0_std=0.5, c0_std=0.5),
+    wl.GRU_3L.scaled(bidir=True, layers=2, T=15, B=140, in_dim=24, hidden=40, varlen=(1, 15)),
+]
+
+
+@pytest.mark.parametrize("spec", CLUSTER, ids=lambda s: f"{s.name}-T{s.T}-B{s.B}-H{s.hidden}")
+def test_cluster_resident_kernel(spec):
+    """W_hh resident in one thread-block cluster, h exchanged through
+    distributed shared memory, clusters on disjoint batch slices."""
+    inp = wl.make_rnn_inputs(spec, seed=19)
+    dev = torch.device("cuda")
+    net = binding.RNN.from_spec(spec)
+    net.set_attr(binding.RCU_ATTR_FORCE_PATH, 3)
+    net.set_attr(binding.RCU_ATTR_PROFILE, 1)
+    net.set_weights(inp["weights"])
+    lengths = inp["lengths"].to(dev) if inp["lengths"] is not None else None
+    h0 = inp["h0"].to(dev) if inp["h0"] is not None else None
+    c0 = inp["c0"].to(dev) if inp["c0"] is not None else None
+    y, hn, cn = net.forward(inp["x"].to(dev), lengths=lengths, h0=h0, c0=c0)
+    assert net.status() == 0
+    torch.cuda.synchronize()
+    assert "recurrent_cluster" in net.profile()
+    got = (y.cpu().numpy(), hn.cpu().numpy(), None if cn is None else cn.cpu().numpy())
+    compare(spec, got, run_oracle(spec, inp))
+    net.close()
+
+
 @pytest.mark.parametrize("ksplit", [1, 2])
 def test_barrier_timeout_on_tensor_core_path(ksplit):
     spec = wl.GRU_3L.scaled(layers=1, T=4, B=20, in_dim=16, hidden=128)
