@@ -27,6 +27,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc_common.cuh"
 
 namespace rcu {
 
@@ -111,6 +112,52 @@ __device__ __forceinline__ void chunk_matmul(const WT *Wsm, int Rx, int Kx, cons
   }
 }
 
+// Row-major variant (fp32 exchange): hs[i][k] with row stride HS = Kx + 4
+// floats (the 16-byte pad puts 8 consecutive rows on distinct banks), filled
+// by bulk asynchronous copies.  A thread's 4 rows are ii, ii + CB/4, ...,
+// so the lanes of one load touch consecutive rows.  red as in chunk_matmul.
+template <typename WT>
+__device__ __forceinline__ void chunk_matmul_rm(const WT *Wsm, int Rx, int Kx, const float *hs,
+                                                int HS, int CB, float *red, Split sp) {
+  const int tid = threadIdx.x;
+  if (tid >= sp.tiles * sp.ks) return;
+  const int tile = tid % sp.tiles, ks = tid / sp.tiles;
+  const int nrt = Rx / 4;
+  const int ir = tile % nrt, ii = tile / nrt;
+  const int k0 = ks * sp.kc, k1 = min(Kx, k0 + sp.kc);
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  const int rs = CB / 4;  // row stride between a thread's rows
+  const float *hp = hs + (size_t)ii * HS;
+  const WT *wp = Wsm + ir * 4;
+#pragma unroll 2
+  for (int k = k0; k < k1; k += 4) {
+    float4 hv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      hv[i] = *reinterpret_cast<const float4 *>(hp + (size_t)i * rs * HS + k);
+    float w[4][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) load4(wp + (size_t)(k + q) * Rx, w[q]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float h4[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(h4[q], w[q][j], acc[i][j]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float4 v = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    *reinterpret_cast<float4 *>(red + ((size_t)(ks * CB + ii + i * rs)) * Rx + ir * 4) = v;
+  }
+}
+
 // hs[k][i] = src[(row0 + i) * ld + k] for i < nr (0 for i >= nr), k < Kx.
 // Loads are issued LB at a time into registers before any store, so their L2
 // latencies overlap.
@@ -146,8 +193,12 @@ __device__ __forceinline__ float red_sum(const float *red, int ks, int CB, int R
 }
 
 struct Smem {
-  size_t ws, wr, hs, red, st, bsz, total;
+  size_t ws, wr, hs, red, st, bsz, mbar, total;
 };
+// fp32 exchange without projection: h rows arrive by bulk copy, row-major
+__host__ __device__ inline bool rowmajor_h(const RecParams &p, size_t wsz) {
+  return wsz == 4 && p.proj == 0;
+}
 __host__ __device__ inline Smem smem_layout(const RecParams &p, size_t wsz) {
   const bool proj = p.proj > 0;
   Smem L;
@@ -159,7 +210,10 @@ __host__ __device__ inline Smem smem_layout(const RecParams &p, size_t wsz) {
   o = round_up_sz(o, 16);
   L.hs = o;
   const int Kh = p.Kp > (proj ? p.Hp : 0) ? p.Kp : p.Hp;
-  o += (size_t)Kh * p.CB * 4;
+  if (rowmajor_h(p, wsz))
+    o += (size_t)p.CB * (p.Kp + 4) * 4;
+  else
+    o += (size_t)Kh * p.CB * 4;
   L.red = o;
   const Split s1 = make_split(p.CB, p.Rp, p.Kp);
   size_t red = (size_t)s1.ks * p.CB * p.Rp;
@@ -172,6 +226,9 @@ __host__ __device__ inline Smem smem_layout(const RecParams &p, size_t wsz) {
   if (!proj && (size_t)p.B * p.U <= STATE_SMEM_MAX) o += (size_t)2 * p.B * p.U * 4;
   L.bsz = o;
   if (p.T <= BSZ_SMEM_MAX) o += (size_t)p.T * 4;
+  o = round_up_sz(o, 8);
+  L.mbar = o;
+  o += 16;
   L.total = o;
   return L;
 }
@@ -194,6 +251,17 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
   WT *Wr = reinterpret_cast<WT *>(smem + L.wr);
   float *hs = reinterpret_cast<float *>(smem + L.hs);
   float *red = reinterpret_cast<float *>(smem + L.red);
+  const bool rm = rowmajor_h(p, sizeof(WT));
+  uint64_t *hbar = reinterpret_cast<uint64_t *>(smem + L.mbar);
+  __shared__ int s_abort, s_ok;
+  uint32_t hphase = 0;
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    if (rm) {
+      tc::mbar_init(hbar, 1);
+      tc::fence_mbar_init();
+    }
+  }
 
   {  // resident weights
     const WT *gW = reinterpret_cast<const WT *>(p.Whh[d]) + (size_t)ug * Kp * p.Rp;
@@ -309,10 +377,39 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
     for (int cb = 0; cb < nact; cb += CB) {
       const int nr = min(CB, nact - cb);
       __syncthreads();
-      load_chunk_T(hcur, Kp, cb, nr, Kp, CB, hs);
+      if (rm) {
+        // rows [cb, cb+nr) of h_{t-1} by bulk copy (the exchange buffer was
+        // written through the generic proxy and acquired at the step barrier)
+        if (threadIdx.x < 32) {
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          if (threadIdx.x == 0) tc::mbar_arrive_expect_tx(hbar, (uint32_t)(nr * Kp * 4));
+          __syncwarp();
+          for (int i = threadIdx.x; i < nr; i += 32)
+            tc::bulk_load(hs + (size_t)i * (Kp + 4), hcur + (size_t)(cb + i) * Kp,
+                          (uint32_t)(Kp * 4), hbar);
+        }
+        if (threadIdx.x == 0)
+          s_ok = tc::mbar_wait(hbar, hphase & 1u, p.err, &s_abort, p.timeout_ns);
+        ++hphase;
+        __syncthreads();
+        if (!s_ok) {
+          // let the copies land before the CTA leaves (bounded, ignores the abort)
+          if (threadIdx.x == 0) {
+            volatile int never = 0;
+            tc::mbar_wait(hbar, (hphase - 1) & 1u, nullptr, &never, 100000000ull);
+          }
+          __syncthreads();
+          return;
+        }
+        if (tr && cb == 0) p.trace[step * 16 + 3] = globaltimer_ns();
+        chunk_matmul_rm(Ws, p.Rp, Kp, hs, Kp + 4, CB, red, sp1);
+      } else {
+        load_chunk_T(hcur, Kp, cb, nr, Kp, CB, hs);
+        __syncthreads();
+        chunk_matmul(Ws, p.Rp, Kp, hs, CB, red, sp1);
+      }
       __syncthreads();
-      chunk_matmul(Ws, p.Rp, Kp, hs, CB, red, sp1);
-      __syncthreads();
+      if (tr && cb == 0) p.trace[step * 16 + 4] = globaltimer_ns();
       const bool pre = have_pre && cb == 0;
       for (int e = threadIdx.x; e < nr * U; e += NT) {
         const int i = e / U, j = e % U, u = u0 + j;
@@ -367,6 +464,8 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
       }
     }
     if (tr) p.trace[step * 16 + 1] = globaltimer_ns();
+    // h_t is read by bulk copies (async proxy) in the next step
+    if (rm) asm volatile("fence.proxy.async.global;" ::: "memory");
     // publish h_t first; the outputs and the next step's G loads follow the
     // arrival, so its release does not wait for them
     group_arrive(ctr);
