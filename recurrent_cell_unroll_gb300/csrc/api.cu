@@ -551,11 +551,11 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
     if (!done) {
       cudaError_t e = bf ? launch_gemm_simt<__nv_bfloat16, __nv_bfloat16>(
                                (const __nv_bfloat16 *)X, ldx, (const __nv_bfloat16 *)h->wih[l].p,
-                               ldw, (const float *)h->gbias[l].p, G, N, Mmax, M_dev, N, K, s)
+                               ldw, (const float *)h->gbias[l].p, G, N, Mmax, M_dev, N, K, s, err)
                          : launch_gemm_simt<float, float>((const float *)X, ldx,
                                                           (const float *)h->wih[l].p, ldw,
                                                           (const float *)h->gbias[l].p, G, N,
-                                                          Mmax, M_dev, N, K, s);
+                                                          Mmax, M_dev, N, K, s, err);
       if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "gemm: %s", cudaGetErrorString(e));
     }
     h->end(s);
@@ -716,6 +716,7 @@ static int status_from_dev(int v) {
     case DEV_OK: return RCU_OK;
     case DEV_TIMEOUT: return fail(RCU_ERR_TIMEOUT, "device step barrier timed out");
     case DEV_LENGTHS: return fail(RCU_ERR_LENGTHS, "a length was outside [1, T]");
+    case DEV_CONFIG: return fail(RCU_ERR_CUDA, "a cluster kernel ran without its cluster shape");
     default: return fail(RCU_ERR_CUDA, "unknown device status %d", v);
   }
 }

@@ -8,7 +8,10 @@
 namespace rcu {
 
 // Device-side error words (one int per handle workspace).
-enum DevErr : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_LENGTHS = 2 };
+// DEV_CONFIG: a kernel that exchanges data between the CTAs of a thread-block
+// cluster found itself launched with another cluster shape, and returned
+// before touching any peer's shared memory.
+enum DevErr : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_LENGTHS = 2, DEV_CONFIG = 3 };
 
 enum Cell : int { CELL_LSTM = 0, CELL_GRU = 1 };
 

@@ -29,7 +29,15 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const XT *__restrict__ X,
                                                        const float *__restrict__ bias,
                                                        float *__restrict__ G, int ldg, int M,
                                                        const int32_t *__restrict__ M_dev, int N,
-                                                       int K, int kchunk) {
+                                                       int K, int kchunk, int *err) {
+  if (gridDim.z > 1) {
+    uint32_t ncta;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(ncta));
+    if (ncta != gridDim.z) {  // the K slices must share one cluster
+      if (err && threadIdx.x == 0) atomicCAS(err, DEV_OK, DEV_CONFIG);
+      return;
+    }
+  }
   if (M_dev) M = *M_dev;
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
   // every CTA of a K-split cluster shares (m0, n0), so they leave together
@@ -155,7 +163,7 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const XT *__restrict__ X,
 template <typename XT, typename WT>
 cudaError_t launch_gemm_simt(const XT *X, int ldx, const WT *W, int ldw, const float *bias,
                              float *G, int ldg, int M, const int32_t *M_dev, int N, int K,
-                             cudaStream_t s) {
+                             cudaStream_t s, int *err) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   dim3 grid(ceil_div(N, BN), ceil_div(M, BM));
   const int tiles = (int)(grid.x * grid.y);
@@ -185,18 +193,19 @@ cudaError_t launch_gemm_simt(const XT *X, int ldx, const WT *W, int ldw, const f
     cfg.attrs = a;
     cfg.numAttrs = 1;
     int kc = kchunk;
-    void *args[] = {&X, &ldx, &W, &ldw, &bias, &G, &ldg, &M, &M_dev, &N, &K, &kc};
+    void *args[] = {&X, &ldx, &W, &ldw, &bias, &G, &ldg, &M, &M_dev, &N, &K, &kc, &err};
     return cudaLaunchKernelExC(&cfg, fn, args);
   }
-  gemm_simt_kernel<XT, WT><<<grid, NT, 0, s>>>(X, ldx, W, ldw, bias, G, ldg, M, M_dev, N, K, K);
+  gemm_simt_kernel<XT, WT><<<grid, NT, 0, s>>>(X, ldx, W, ldw, bias, G, ldg, M, M_dev, N, K, K,
+                                                 err);
   return cudaGetLastError();
 }
 
 template cudaError_t launch_gemm_simt<float, float>(const float *, int, const float *, int,
                                                     const float *, float *, int, int,
-                                                    const int32_t *, int, int, cudaStream_t);
+                                                    const int32_t *, int, int, cudaStream_t, int *);
 template cudaError_t launch_gemm_simt<__nv_bfloat16, __nv_bfloat16>(
     const __nv_bfloat16 *, int, const __nv_bfloat16 *, int, const float *, float *, int, int,
-    const int32_t *, int, int, cudaStream_t);
+    const int32_t *, int, int, cudaStream_t, int *);
 
 }  // namespace rcu

@@ -40,9 +40,11 @@ cudaError_t launch_convert(const float *src, OT *dst, size_t n, cudaStream_t s);
 // G[m, n] = sum_k X[m, k] * W[n, k] + bias[n] for m < *M_dev (or M when M_dev
 // is NULL).  Row-major; ldx/ldw/ldg are row strides in elements.
 template <typename XT, typename WT>
+// err: device error word (DEV_CONFIG if a K-split cluster launch ran with
+// another cluster shape), or NULL.
 cudaError_t launch_gemm_simt(const XT *X, int ldx, const WT *W, int ldw, const float *bias,
                              float *G, int ldg, int M, const int32_t *M_dev, int N, int K,
-                             cudaStream_t s);
+                             cudaStream_t s, int *err);
 
 // ---- recurrent_simt.cu -------------------------------------------------------
 struct RecParams {

@@ -201,7 +201,7 @@ extern "C" int rnn_lstm_forward_noalloc(int T, int B, int in_dim, int hidden, co
     return set_error(RCU_ERR_CUDA, cudaGetErrorString(e));
   bias_sum_kernel<<<(4 * H + 255) / 256, 256, 0, s>>>(b_ih, b_hh, bias, 4 * H);
   if ((e = launch_gemm_simt<float, float>(x, in_dim, W_ih, in_dim, bias, G, 4 * H, T * B,
-                                           nullptr, 4 * H, in_dim, s)) != cudaSuccess)
+                                           nullptr, 4 * H, in_dim, s, p.err)) != cudaSuccess)
     return set_error(RCU_ERR_CUDA, cudaGetErrorString(e));
   const size_t smem = smem_of(p.CB);
   if ((e = cudaFuncSetAttribute((const void *)lstm_noalloc_kernel,

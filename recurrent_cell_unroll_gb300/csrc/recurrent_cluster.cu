@@ -97,9 +97,13 @@ __device__ __forceinline__ float4 wload(const __nv_bfloat16 *p) {
 template <typename WT, int NG>
 __global__ void __launch_bounds__(NT, 1)
     rec_cluster_kernel(const RecParams p, const void *W0, const void *W1, int U, int Kc, int Bc,
-                       int NCL) {
+                       int NCL, int cs_plan) {
   extern __shared__ __align__(16) unsigned char smem[];
   const uint32_t cs = cl_size(), rank = cl_rank();
+  if ((int)cs != cs_plan) {  // units are assigned for cs_plan CTAs per cluster
+    if (threadIdx.x == 0) atomicCAS(p.err, DEV_OK, DEV_CONFIG);
+    return;
+  }
   const int ci = blockIdx.x / cs;
   const int d = ci / NCL, slice = ci % NCL;
   const int B = p.B, H = p.H, Hout = p.Hout;
@@ -352,8 +356,9 @@ cudaError_t launch_recurrent_cluster(const RecParams &p, const ClusterRecPlan &c
   cfg.attrs = a;
   cfg.numAttrs = 1;
   RecParams pc = p;
-  int U = cp.U, Kc = cp.Kc, Bc = cp.Bc, NCL = cp.NCL;
-  void *args[] = {&pc, const_cast<void **>(&W0), const_cast<void **>(&W1), &U, &Kc, &Bc, &NCL};
+  int U = cp.U, Kc = cp.Kc, Bc = cp.Bc, NCL = cp.NCL, cs = cp.cs;
+  void *args[] = {&pc, const_cast<void **>(&W0), const_cast<void **>(&W1), &U, &Kc, &Bc, &NCL,
+                  &cs};
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 

@@ -110,6 +110,11 @@ template <int NG, int KS>
 __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ Maps maps,
                                                        const RecParams p) {
   static_assert(KS == 1 || KS == 2, "K is split over one or two CTAs");
+  if (KS > 1 && tc::cluster_nctarank() != (uint32_t)KS) {
+    // the K split needs its partner CTA: never address a peer that is not there
+    if (threadIdx.x == 0) atomicCAS(p.err, DEV_OK, DEV_CONFIG);
+    return;
+  }
   constexpr int NTOT = NG * UNITS * KS;
   constexpr uint32_t TCOLS = NTOT <= 64 ? 64 : (NTOT <= 128 ? 128 : 256);
   extern __shared__ uint8_t smem_raw[];
