@@ -107,8 +107,7 @@ __device__ __forceinline__ float tanh_fast(float x) {
 __device__ __forceinline__ float sigmoid_fast(float x) { return fmaf(0.5f, tanh_fast(0.5f * x), 0.5f); }
 
 template <int NG, int KS>
-__global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ Maps maps,
-                                                       const RecParams p) {
+__device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p) {
   static_assert(KS == 1 || KS == 2, "K is split over one or two CTAs");
   if (KS > 1 && tc::cluster_nctarank() != (uint32_t)KS) {
     // the K split needs its partner CTA: never address a peer that is not there
@@ -522,6 +521,19 @@ __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ M
   }
 }
 
+// K kept whole (optionally with a multicast cluster chosen at launch)
+template <int NG>
+__global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ Maps maps,
+                                                       const RecParams p) {
+  rec_tc_body<NG, 1>(maps, p);
+}
+// K split over a CTA pair; the pair is the kernel's own cluster shape
+template <int NG>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT, 1)
+    rec_tc_pair_kernel(const __grid_constant__ Maps maps, const RecParams p) {
+  rec_tc_body<NG, 2>(maps, p);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -586,16 +598,17 @@ namespace {
 
 template <int NG>
 const void *kernel_for(int ks) {
-  return ks == 2 ? (const void *)rec_tc_kernel<NG, 2> : (const void *)rec_tc_kernel<NG, 1>;
+  return ks == 2 ? (const void *)rec_tc_pair_kernel<NG> : (const void *)rec_tc_kernel<NG>;
 }
 
 // Cooperative launch of `grid` CTAs in clusters of `cs`; false (nothing
-// launched) when that cluster grid cannot be resident at once.
+// launched) when that cluster grid cannot be resident at once.  `fixed`: the
+// kernel declares its cluster shape itself (then no launch attribute names it).
 bool launch_clustered(const void *fn, int grid, int cs, size_t smem, void **args, cudaStream_t s,
-                      cudaError_t *err) {
+                      cudaError_t *err, bool fixed = false) {
   *err = cudaSuccess;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-      cudaSuccess) {
+  if (!fixed &&
+      cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
     cudaGetLastError();
     return false;
   }
@@ -616,10 +629,15 @@ bool launch_clustered(const void *fn, int grid, int cs, size_t smem, void **args
   int max_clusters = 0;
   cudaLaunchConfig_t q = cfg;
   q.numAttrs = 1;  // occupancy query on the cluster shape
+  if (fixed) q.numAttrs = 0;
   if (cudaOccupancyMaxActiveClusters(&max_clusters, fn, &q) != cudaSuccess ||
       (long long)max_clusters * cs < grid) {
     cudaGetLastError();
     return false;
+  }
+  if (fixed) {  // cooperative attribute only; the cluster shape is the kernel's
+    attr[0] = attr[1];
+    cfg.numAttrs = 1;
   }
   *err = cudaLaunchKernelExC(&cfg, fn, args);
   return true;
@@ -660,7 +678,7 @@ cudaError_t launch_tc_recurrent(const TcRecParams &tp, int nsm, cudaStream_t s) 
     const int grid = p.D * NBG * p.NU;
     void *args[] = {&maps, &p};
     if (ks == 2) {
-      if (launch_clustered(fn, grid, 2, geo.smem, args, s, &e)) return e;
+      if (launch_clustered(fn, grid, 2, geo.smem, args, s, &e, true)) return e;
       ks = 1;  // the pair grid cannot be co-resident: no split
       continue;
     }
