@@ -192,7 +192,7 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- our arm
 
-def make_runner(spec, inp, dev):
+def make_runner(spec, inp, dev, tc_ksplit=0):
     from recurrent_cell_unroll_gb300 import binding
     if isinstance(spec, wl.RssmSpec):
         m = binding.RSSM(spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden)
@@ -225,6 +225,8 @@ def make_runner(spec, inp, dev):
         return step, launches, profile_on, profile_read, e2e_io, status, m
 
     net = binding.RNN.from_spec(spec)
+    if tc_ksplit:
+        net.set_attr(binding.RCU_ATTR_TC_KSPLIT, tc_ksplit)
     net.set_weights(inp["weights"], device=dev)
     d = {k: (None if inp[k] is None else inp[k].to(dev)) for k in ("x", "lengths", "h0", "c0")}
     T, B = spec.T, spec.B
@@ -304,7 +306,8 @@ def run_ours(args, spec, rank, local, ws):
     binding.load()
     inp = (wl.make_rssm_inputs(spec, seed=args.seed + rank) if isinstance(spec, wl.RssmSpec)
            else wl.make_rnn_inputs(spec, seed=args.seed + rank))
-    step, launches, profile_on, profile_read, e2e_io, status, keep = make_runner(spec, inp, dev)
+    step, launches, profile_on, profile_read, e2e_io, status, keep = make_runner(
+        spec, inp, dev, args.tc_ksplit)
     nsm = torch.cuda.get_device_properties(dev).multi_processor_count
     flush = torch.empty(int(2 * L2_BYTES // 4), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -542,6 +545,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--T", type=int, default=0,
                     help="override the sequence length (small cases for profiler captures)")
+    ap.add_argument("--tc-ksplit", type=int, default=0, choices=[0, 1, 2],
+                    help="tensor-core recurrence: CTAs splitting K (0 = the library's choice)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
