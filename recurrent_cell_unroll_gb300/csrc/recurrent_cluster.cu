@@ -14,9 +14,14 @@
 //   2. adds the input projection G (prefetched during the previous step),
 //      applies the gates and the cell update (c and h stay in registers, one
 //      (row, unit) pair per thread);
-//   3. stores h_t into the h buffer of every CTA of the cluster (distributed
-//      shared memory, double-buffered by step parity) and crosses the step
-//      with barrier.cluster (release/acquire), writing y after its arrival.
+//   3. stores h_t into the h buffer of every CTA of the cluster with
+//      asynchronous distributed-shared-memory stores (st.async), each
+//      signalling its bytes on the receiving CTA's mbarrier for that buffer
+//      (double-buffered by step parity).  A CTA starts step t+1 as soon as
+//      all bytes of h_t have landed in its own buffer: no cluster-wide
+//      barrier and no release fence per step.  A peer can write h_{t+1}
+//      into the buffer this CTA reads at step t only after receiving this
+//      CTA's h_t, which is sent after that read.
 // Rows whose length is exhausted leave the active prefix of the sorted batch
 // ("RNN Op Changes", apache/mxnet issue 9543); the backward direction runs
 // row s at time len_s - 1 - step.
@@ -24,6 +29,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc_common.cuh"
 
 namespace rcu {
 
@@ -37,7 +43,7 @@ constexpr int SMEM_LIMIT = 227 * 1024;
 constexpr int SOFF_MAX = 4096;  // step offsets staged in shared memory up to this T
 
 struct CSmem {
-  size_t w, h, pre, lens, soff, total;
+  size_t w, h, pre, lens, soff, bar, total;
 };
 __host__ __device__ inline CSmem cl_smem(int R, int Kc, int Bc, size_t es, int T) {
   CSmem L;
@@ -53,6 +59,9 @@ __host__ __device__ inline CSmem cl_smem(int R, int Kc, int Bc, size_t es, int T
   o += (size_t)Bc * 4;
   L.soff = o;
   if (T <= SOFF_MAX) o += (size_t)T * 4;
+  o = round_up_sz(o, 8);
+  L.bar = o;
+  o += 16;  // one mbarrier per h buffer
   L.total = o;
   return L;
 }
@@ -73,15 +82,24 @@ __device__ __forceinline__ void cl_arrive() {
 __device__ __forceinline__ void cl_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ uint32_t cl_map(const void *p, uint32_t rank) {
+__device__ __forceinline__ uint32_t cl_map_addr(uint32_t smem_addr, uint32_t rank) {
   uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-               : "=r"(r)
-               : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
   return r;
+}
+__device__ __forceinline__ uint32_t cl_map(const void *p, uint32_t rank) {
+  return cl_map_addr((uint32_t)__cvta_generic_to_shared(p), rank);
 }
 __device__ __forceinline__ void st_cl(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// 4-byte asynchronous store into a cluster CTA's shared memory, completing as
+// 4 bytes of complete_tx on that CTA's mbarrier
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                   addr),
+               "r"(__float_as_uint(v)), "r"(bar)
+               : "memory");
 }
 
 __device__ __forceinline__ float4 wload(const float *p) {
@@ -119,6 +137,8 @@ __global__ void __launch_bounds__(NT, 1)
   float *pre = reinterpret_cast<float *>(smem + L.pre);  // [Bc][R]
   int *slens = reinterpret_cast<int *>(smem + L.lens);   // [Bc] lengths of the slice's rows
   int *ssoff = reinterpret_cast<int *>(smem + L.soff);   // [T] packed row offset of each step
+  uint64_t *hbar = reinterpret_cast<uint64_t *>(smem + L.bar);  // [2] h buffer arrivals
+  __shared__ int s_ok;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int grp = lane / 8, gl = lane % 8;
 
@@ -131,6 +151,11 @@ __global__ void __launch_bounds__(NT, 1)
     for (size_t i = threadIdx.x; i < n16; i += NT)
       dst[i] = i < v16 ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
     for (int i = threadIdx.x; i < 2 * Bc * Kc; i += NT) hb[i] = 0.f;
+    if (threadIdx.x == 0) {
+      tc::mbar_init(&hbar[0], 1);
+      tc::mbar_init(&hbar[1], 1);
+      tc::fence_mbar_init();
+    }
   }
   const int32_t *sidx = p.meta.sorted_idx;
   const int32_t *lens = p.meta.lens_sorted;
@@ -167,25 +192,40 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
     for (int q = 0; q < NG; ++q) gx[q] = __ldg(g + (size_t)q * H);
   };
-  // every CTA's h buffers are zeroed (and the metadata staged) before any
-  // peer writes into them
+  // every CTA's h buffers are zeroed, its mbarriers initialised (and the
+  // metadata staged) before any peer writes into them
   __syncthreads();
   cl_arrive();
   cl_wait();
+  // bytes each buffer receives per step: every active row's H units from the
+  // whole cluster
+  const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(&hbar[0]);
+  const uint64_t tmo = p.timeout_ns;
+  volatile int never = 0;  // no abort source: only the timeout ends a wait
+  if (threadIdx.x == 0 && nrow > 0) tc::mbar_arrive_expect_tx(&hbar[0], (uint32_t)(nrow * H * 4));
   if (own) {
-    for (uint32_t q = 0; q < cs; ++q) st_cl(cl_map(hb + (size_t)bq * Kc + u, q), hv);
+    for (uint32_t q = 0; q < cs; ++q)
+      st_async_f32(cl_map(hb + (size_t)bq * Kc + u, q), hv, cl_map(&hbar[0], q));
   }
   prefetch(0);
-  cl_arrive();
-  cl_wait();
 
   int nact = nrow;  // active rows: the prefix of the slice with length > step
+  int done = 0;     // steps whose input buffer completed
   for (int step = 0; step < Tcl; ++step) {
     const bool tr = p.trace && blockIdx.x == 0 && threadIdx.x == 0;
-    if (tr) p.trace[step * 16 + 0] = globaltimer_ns();
     while (nact > 0 && slens[nact - 1] <= step) --nact;
-    const float *hcur = hb + (size_t)(step & 1) * Bc * Kc;
-    float *hnxt = hb + (size_t)((step & 1) ^ 1) * Bc * Kc;
+    const int cur = step & 1;
+    const float *hcur = hb + (size_t)cur * Bc * Kc;
+    float *hnxt = hb + (size_t)(cur ^ 1) * Bc * Kc;
+    if (threadIdx.x == 0) {
+      // arm the next buffer for this step's sends, then wait for h_{t-1}
+      tc::mbar_arrive_expect_tx(&hbar[cur ^ 1], (uint32_t)(nact * H * 4));
+      s_ok = tc::mbar_wait(&hbar[cur], (uint32_t)(step >> 1) & 1u, p.err, &never, tmo);
+    }
+    __syncthreads();
+    if (!s_ok) break;
+    done = step + 1;
+    if (tr) p.trace[step * 16 + 0] = globaltimer_ns();
     // ---- h_{t-1} W_hh^T: a group of 8 lanes per output row (4 rows per warp
     //      pass); lane l of a group takes the 16-byte K chunks l, l+8, ...
     for (int b = 0; b < nact; ++b) {
@@ -231,10 +271,11 @@ __global__ void __launch_bounds__(NT, 1)
         hv = (1.f - zg) * ng + zg * hv;
       }
       if (tr) p.trace[step * 16 + 4] = globaltimer_ns();
-      for (uint32_t q = 0; q < cs; ++q) st_cl(cl_map(hnxt + (size_t)bq * Kc + u, q), hv);
+      const uint32_t nb = bar0 + (uint32_t)((cur ^ 1) * 8);
+      for (uint32_t q = 0; q < cs; ++q)
+        st_async_f32(cl_map(hnxt + (size_t)bq * Kc + u, q), hv, cl_map_addr(nb, q));
     }
     if (tr) p.trace[step * 16 + 1] = globaltimer_ns();
-    cl_arrive();
     // outputs and the next step's G loads leave the critical path
     if (act) {
       const int tt = d == 0 ? step : len - 1 - step;
@@ -244,9 +285,18 @@ __global__ void __launch_bounds__(NT, 1)
             Op<WT>::from_f(hv);
     }
     prefetch(step + 1);
-    cl_wait();
-    if (tr) p.trace[step * 16 + 2] = globaltimer_ns();
   }
+  // The last step's h (or, after a failed wait, the pending one) may still
+  // be landing here: wait for it (bounded), and leave only when every CTA of
+  // the cluster has stopped sending.
+  if (threadIdx.x == 0 && Tcl > 0) {
+    const int ph = done;  // the step whose input buffer is still armed
+    volatile int keep_waiting = 0;  // (a timed-out wait above has set `never`)
+    tc::mbar_wait(&hbar[ph & 1], (uint32_t)(ph >> 1) & 1u, nullptr, &keep_waiting, 100000000ull);
+  }
+  __syncthreads();
+  cl_arrive();
+  cl_wait();
   if (own) {
     if (p.h_n) p.h_n[((size_t)d * B + borig) * Hout + u] = hv;
     if (NG == 4 && p.c_n) p.c_n[((size_t)d * B + borig) * H + u] = c;
@@ -295,8 +345,8 @@ bool plan_recurrent_cluster(ClusterRecPlan *cp, int cell, int H, int Hout, int T
     // the batch slice: as many co-resident clusters as the GPU holds, then
     // the smallest slice that covers B
     const size_t smem1 = cl_smem(nG * U, Kc, 1, es, T).total;
-    if (smem1 > (size_t)SMEM_LIMIT) continue;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT) !=
+    if (smem1 > (size_t)SMEM_LIMIT - 1024) continue;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1) !=
         cudaSuccess) {
       cudaGetLastError();
       continue;
@@ -321,7 +371,7 @@ bool plan_recurrent_cluster(ClusterRecPlan *cp, int cell, int H, int Hout, int T
     const int Bc = ceil_div(std::max(B, 1), per_dir);
     if (Bc > max_rows || Bc * U > NT) continue;
     const size_t smem = cl_smem(nG * U, Kc, Bc, es, T).total;
-    if (smem > (size_t)SMEM_LIMIT) continue;
+    if (smem > (size_t)SMEM_LIMIT - 1024) continue;  // room for the kernel's static shared memory
     cp->cs = cs;
     cp->U = U;
     cp->Kc = Kc;
