@@ -32,11 +32,15 @@ namespace {
 constexpr int RC = 8;    // CTAs per cluster
 constexpr int NT = 512;
 constexpr int MAXBC = 8; // batch rows per cluster
-constexpr int KS_MAX = 8;
+constexpr int KS_MAX = 16;
 constexpr size_t PRELOAD_MAX = 32 * 1024;  // bytes of actions+eps kept in shared memory
+
+__host__ __device__ inline int r4(int v) { return (v + 3) & ~3; }
 
 struct Dims {
   int S, A, Hd, RH, Ha, Ua, Sa, Bc;
+  // padded widths (multiples of 4 floats, so rows start 16-byte aligned)
+  int Hap, U3p, S2p, Hdp, RHp, SAp;
 };
 
 __host__ __device__ inline Dims make_dims(int S, int A, int Hd, int RH, int Bc) {
@@ -46,20 +50,28 @@ __host__ __device__ inline Dims make_dims(int S, int A, int Hd, int RH, int Bc) 
   d.Ua = ceil_div(RH, RC);
   d.Sa = ceil_div(S, RC);
   d.Bc = Bc;
+  d.Hap = r4(d.Ha);
+  d.U3p = r4(3 * d.Ua);
+  d.S2p = r4(2 * d.Sa);
+  d.Hdp = r4(Hd);
+  d.RHp = r4(RH);
+  d.SAp = r4(S + A);
   return d;
 }
 
-__host__ __device__ inline int split_of(int O, int nr, int K) {
-  int ks = NT / (O * nr > 0 ? O * nr : 1);
+// K split of a mat-vec with Op outputs (4 per thread) over K inputs
+__host__ __device__ inline int split_of(int Op, int K) {
+  int ks = NT / (Op / 4 > 0 ? Op / 4 : 1);
   if (ks > KS_MAX) ks = KS_MAX;
-  if (ks > K) ks = K;
+  const int k4 = ceil_div(K, 4);
+  if (ks > k4) ks = k4;
   return ks < 1 ? 1 : ks;
 }
 
 // shared-memory carve-up (floats)
 struct Layout {
-  size_t w1, b1, wih, whh, bih, bhh, w2, b2, w3, b3;  // weights (transposed [k][o])
-  size_t st, av, bel, qv;                              // vectors, [Bc][width]
+  size_t w1, b1, wih, whh, bih, bhh, w2, b2, w3, b3;  // weights (transposed [k][o], o padded)
+  size_t st, in1, av, bel, qv;                         // vectors, [Bc][padded width]
   size_t part1, part2;                                 // chunk partials
   size_t act, eps;                                     // preloaded actions / noise
   size_t total;
@@ -69,24 +81,25 @@ __host__ __device__ inline Layout make_layout(const Dims &d, int T) {
   Layout L;
   size_t o = 0;
   auto take = [&](size_t n) { size_t r = o; o += (n + 3) & ~size_t(3); return r; };
-  L.w1 = take((size_t)(d.S + d.A) * d.Ha);
-  L.b1 = take(d.Ha);
-  L.wih = take((size_t)d.Hd * 3 * d.Ua);
-  L.whh = take((size_t)d.RH * 3 * d.Ua);
-  L.bih = take(3 * d.Ua);
-  L.bhh = take(3 * d.Ua);
-  L.w2 = take((size_t)d.RH * d.Ha);
-  L.b2 = take(d.Ha);
-  L.w3 = take((size_t)d.Hd * 2 * d.Sa);
-  L.b3 = take(2 * d.Sa);
+  L.w1 = take((size_t)(d.S + d.A) * d.Hap);
+  L.b1 = take(d.Hap);
+  L.wih = take((size_t)d.Hd * d.U3p);
+  L.whh = take((size_t)d.RH * d.U3p);
+  L.bih = take(d.U3p);
+  L.bhh = take(d.U3p);
+  L.w2 = take((size_t)d.RH * d.Hap);
+  L.b2 = take(d.Hap);
+  L.w3 = take((size_t)d.Hd * d.S2p);
+  L.b3 = take(d.S2p);
   L.st = take((size_t)d.Bc * d.S);
-  L.av = take((size_t)d.Bc * d.Hd);
-  L.bel = take((size_t)2 * d.Bc * d.RH);
-  L.qv = take((size_t)d.Bc * d.Hd);
-  L.part1 = take((size_t)KS_MAX * d.Bc * 3 * d.Ua > (size_t)KS_MAX * d.Bc * d.Ha
-                     ? (size_t)KS_MAX * d.Bc * 3 * d.Ua
-                     : (size_t)KS_MAX * d.Bc * (d.Ha > 2 * d.Sa ? d.Ha : 2 * d.Sa));
-  L.part2 = take((size_t)KS_MAX * d.Bc * 3 * d.Ua);
+  L.in1 = take((size_t)d.Bc * d.SAp);
+  L.av = take((size_t)d.Bc * d.Hdp);
+  L.bel = take((size_t)2 * d.Bc * d.RHp);
+  L.qv = take((size_t)d.Bc * d.Hdp);
+  int wmax = d.Hap > d.U3p ? d.Hap : d.U3p;
+  if (d.S2p > wmax) wmax = d.S2p;
+  L.part1 = take((size_t)KS_MAX * d.Bc * wmax);
+  L.part2 = take((size_t)KS_MAX * d.Bc * d.U3p);
   const size_t pre = (size_t)T * d.Bc * (d.A + d.S);
   L.preload = pre * 4 <= PRELOAD_MAX;
   L.act = take(L.preload ? (size_t)T * d.Bc * d.A : 0);
@@ -100,43 +113,63 @@ __device__ __forceinline__ float softplus_f(float v) {
   return fmaxf(v, 0.f) + log1pf(expf(-fabsf(v)));
 }
 
-// part[q][r][o] = sum over K-chunk q of Wt[k*O + o] * V[r*ldv + k], for
-// o < O, r < NR, q < ks.  Thread t = (o, q) with o fastest covers every row:
-// each weight is read once and used NR times, the V reads are broadcasts, and
-// the NR x 2 accumulators are independent.
+// part[q][r][o] = sum over K-chunk q of Wt[k*Op + o] * V[r*ldv + k], for
+// o < Op, r < NR, q < ks.  Thread t = (4-output group, q): per 4 inputs it
+// loads a 4x4 weight block and each row's 4 inputs as 16-byte vectors
+// (broadcast across the group) and does 16*NR FMAs, so shared-memory traffic
+// stays below the FMA rate.  Op, ldv and the chunk starts are multiples of 4.
 template <int NR>
-__device__ __forceinline__ void matvec_part(const float *Wt, int O, int K, const float *V,
+__device__ __forceinline__ void matvec_part(const float *Wt, int Op, int K, const float *V,
                                             int ldv, int ks, float *part) {
-  const int n = O * ks;
-  const int kc = ceil_div(K, ks);
+  const int ng = Op / 4;
+  const int n = ng * ks;
+  const int kc = ceil_div(ceil_div(K, ks), 4) * 4;
   for (int t = threadIdx.x; t < n; t += NT) {
-    const int o = t % O, q = t / O;
+    const int og = t % ng, q = t / ng;
     const int k0 = q * kc, k1 = min(K, k0 + kc);
-    float a[NR][2];
+    float a[NR][4];
 #pragma unroll
-    for (int r = 0; r < NR; ++r) a[r][0] = a[r][1] = 0.f;
+    for (int r = 0; r < NR; ++r) a[r][0] = a[r][1] = a[r][2] = a[r][3] = 0.f;
+    const float *wp = Wt + og * 4;
     int k = k0;
-    for (; k + 1 < k1; k += 2) {
-      const float w0 = Wt[(size_t)k * O + o], w1 = Wt[(size_t)(k + 1) * O + o];
+    for (; k + 3 < k1; k += 4) {
+      float4 w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w[i] = *reinterpret_cast<const float4 *>(wp + (size_t)(k + i) * Op);
 #pragma unroll
       for (int r = 0; r < NR; ++r) {
-        a[r][0] = fmaf(w0, V[(size_t)r * ldv + k], a[r][0]);
-        a[r][1] = fmaf(w1, V[(size_t)r * ldv + k + 1], a[r][1]);
+        const float4 v = *reinterpret_cast<const float4 *>(V + (size_t)r * ldv + k);
+        const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          a[r][0] = fmaf(vv[i], w[i].x, a[r][0]);
+          a[r][1] = fmaf(vv[i], w[i].y, a[r][1]);
+          a[r][2] = fmaf(vv[i], w[i].z, a[r][2]);
+          a[r][3] = fmaf(vv[i], w[i].w, a[r][3]);
+        }
       }
     }
-    if (k < k1) {
-      const float w0 = Wt[(size_t)k * O + o];
+    for (; k < k1; ++k) {
+      const float4 w = *reinterpret_cast<const float4 *>(wp + (size_t)k * Op);
 #pragma unroll
-      for (int r = 0; r < NR; ++r) a[r][0] = fmaf(w0, V[(size_t)r * ldv + k], a[r][0]);
+      for (int r = 0; r < NR; ++r) {
+        const float v = V[(size_t)r * ldv + k];
+        a[r][0] = fmaf(v, w.x, a[r][0]);
+        a[r][1] = fmaf(v, w.y, a[r][1]);
+        a[r][2] = fmaf(v, w.z, a[r][2]);
+        a[r][3] = fmaf(v, w.w, a[r][3]);
+      }
     }
 #pragma unroll
-    for (int r = 0; r < NR; ++r) part[((size_t)q * NR + r) * O + o] = a[r][0] + a[r][1];
+    for (int r = 0; r < NR; ++r)
+      *reinterpret_cast<float4 *>(part + ((size_t)q * NR + r) * Op + og * 4) =
+          make_float4(a[r][0], a[r][1], a[r][2], a[r][3]);
   }
 }
 
 // Load rows [row0, row0 + n) of a row-major [rows][K] matrix, transposed into
-// shared memory dst[k * ldt + o] (o < n), zero for o in [n, ldt).  Global reads
-// are coalesced along k.
+// shared memory dst[k * ldt + o] (o < n), zero for o in [n, ncols).  Global
+// reads are coalesced along k.
 __device__ __forceinline__ void load_T(const float *src, int K, int row0, int n, int ncols,
                                        int ldt, float *dst) {
   for (int e = threadIdx.x; e < ncols * K; e += NT) {
@@ -161,10 +194,30 @@ __device__ __forceinline__ void flush_outputs(float (&v)[3], float *(&ptr)[3], i
   }
 }
 
-__device__ __forceinline__ float part_sum(const float *part, int O, int nr, int ks, int r, int o) {
-  float a = 0.f;
-  for (int q = 0; q < ks; ++q) a += part[((size_t)q * nr + r) * O + o];
-  return a;
+// part[0][r][o] = sum over q of part[q][r][o], spread over all threads (the
+// consumers then read one value per output instead of ks).  Callers
+// synchronise before and after.
+__device__ __forceinline__ void reduce_parts(float *part, int Op, int nr, int ks) {
+  const int n = nr * Op;
+  for (int e = threadIdx.x; e < n; e += NT) {
+    float a = part[e];
+    for (int q = 1; q < ks; ++q) a += part[(size_t)q * n + e];
+    part[e] = a;
+  }
+}
+// The same for two partial arrays of equal shape in one pass.
+__device__ __forceinline__ void reduce_parts2(float *pa, float *pb, int Op, int nr, int ks) {
+  const int n = nr * Op;
+  for (int e = threadIdx.x; e < 2 * n; e += NT) {
+    float *part = e < n ? pa : pb;
+    const int i = e < n ? e : e - n;
+    float a = part[i];
+    for (int q = 1; q < ks; ++q) a += part[(size_t)q * n + i];
+    part[i] = a;
+  }
+}
+__device__ __forceinline__ float part_sum(const float *part, int Op, int r, int o) {
+  return part[(size_t)r * Op + o];
 }
 
 template <int NR>
@@ -179,6 +232,7 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
   const Dims d = make_dims(p.S, p.A, p.Hd, p.RH, Bc);
   const Layout L = make_layout(d, p.T);
   const int S = d.S, A = d.A, Hd = d.Hd, RH = d.RH, SA = S + A;
+  const int Hdp = d.Hdp, RHp = d.RHp, SAp = d.SAp;
   const int i0 = c * d.Ha, ni = max(0, min(d.Ha, Hd - i0));   // owned a / q outputs
   const int j0 = c * d.Ua, nj = max(0, min(d.Ua, RH - j0));   // owned GRU units
   const int s0 = c * d.Sa, ns = max(0, min(d.Sa, S - s0));    // owned state entries
@@ -186,23 +240,26 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
   const bool tr = p.trace && blockIdx.x == 0 && tid == 0;
   if (tr) p.trace[11] = globaltimer_ns();
 
+  // ---- every padding column and vector starts at zero
+  for (size_t e = tid; e < L.total; e += NT) sm[e] = 0.f;
+  __syncthreads();
   // ---- resident weights, transposed to [k][o]; rows of outputs not owned are zero
-  load_T(p.W1, SA, i0, ni, d.Ha, d.Ha, sm + L.w1);
+  load_T(p.W1, SA, i0, ni, d.Ha, d.Hap, sm + L.w1);
   for (int o = tid; o < d.Ha; o += NT) {
     sm[L.b1 + o] = (o < ni && p.b1) ? p.b1[i0 + o] : 0.f;
     sm[L.b2 + o] = (o < ni && p.b2) ? p.b2[i0 + o] : 0.f;
   }
   for (int g = 0; g < 3; ++g) {
-    load_T(p.Wih, Hd, g * RH + j0, nj, d.Ua, 3 * d.Ua, sm + L.wih + g * d.Ua);
-    load_T(p.Whh, RH, g * RH + j0, nj, d.Ua, 3 * d.Ua, sm + L.whh + g * d.Ua);
+    load_T(p.Wih, Hd, g * RH + j0, nj, d.Ua, d.U3p, sm + L.wih + g * d.Ua);
+    load_T(p.Whh, RH, g * RH + j0, nj, d.Ua, d.U3p, sm + L.whh + g * d.Ua);
   }
   for (int o = tid; o < 3 * d.Ua; o += NT) {
     const int g = o / d.Ua, j = o % d.Ua;
     sm[L.bih + o] = (j < nj && p.bih) ? p.bih[g * RH + j0 + j] : 0.f;
     sm[L.bhh + o] = (j < nj && p.bhh) ? p.bhh[g * RH + j0 + j] : 0.f;
   }
-  load_T(p.W2, RH, i0, ni, d.Ha, d.Ha, sm + L.w2);
-  for (int h = 0; h < 2; ++h) load_T(p.W3, Hd, h * S + s0, ns, d.Sa, 2 * d.Sa, sm + L.w3 + h * d.Sa);
+  load_T(p.W2, RH, i0, ni, d.Ha, d.Hap, sm + L.w2);
+  for (int h = 0; h < 2; ++h) load_T(p.W3, Hd, h * S + s0, ns, d.Sa, d.S2p, sm + L.w3 + h * d.Sa);
   for (int o = tid; o < 2 * d.Sa; o += NT) {
     const int h = o / d.Sa, j = o % d.Sa;
     sm[L.b3 + o] = (j < ns && p.b3) ? p.b3[h * S + s0 + j] : 0.f;
@@ -214,9 +271,9 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
   }
   for (int e = tid; e < Bc * RH; e += NT) {
     const int r = e / RH, k = e % RH;
-    sm[L.bel + e] = (r < nr && p.belief0) ? p.belief0[(size_t)(b0 + r) * RH + k] : 0.f;
+    sm[L.bel + (size_t)r * RHp + k] =
+        (r < nr && p.belief0) ? p.belief0[(size_t)(b0 + r) * RH + k] : 0.f;
   }
-  for (int e = tid; e < Bc * Hd; e += NT) { sm[L.av + e] = 0.f; sm[L.qv + e] = 0.f; }
   if (L.preload) {
     for (int e = tid; e < p.T * Bc * A; e += NT) {
       const int t = e / (Bc * A), r = (e / A) % Bc, k = e % A;
@@ -234,10 +291,10 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
 #pragma unroll
   for (int r = 0; r < RC; ++r) rem[r] = cluster.map_shared_rank(sm, r);
 
-  const int ks1 = split_of(d.Ha, Bc, SA);
-  const int ks2a = split_of(3 * d.Ua, 1, Hd), ks2b = split_of(3 * d.Ua, 1, RH);
-  const int ks3 = split_of(d.Ha, 1, RH);
-  const int ks4 = split_of(2 * d.Sa, 1, Hd);
+  const int ks1 = split_of(d.Hap, SA);
+  const int ks2a = split_of(d.U3p, Hd), ks2b = split_of(d.U3p, RH);
+  const int ks3 = split_of(d.Hap, RH);
+  const int ks4 = split_of(d.S2p, Hd);
   float *part1 = sm + L.part1, *part2 = sm + L.part2;
   float out_v[3] = {0.f, 0.f, 0.f};
   float *out_p[3] = {nullptr, nullptr, nullptr};
@@ -245,57 +302,59 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
   for (int t = 0; t < p.T; ++t) {
     const int cur = t & 1;
     if (tr) p.trace[t * 16 + 0] = globaltimer_ns();
-    float *bel_cur = sm + L.bel + (size_t)cur * Bc * RH;
-    const size_t bel_nxt = L.bel + (size_t)(cur ^ 1) * Bc * RH;
-    // ---- phase 1: a = ELU(W1 [state, action] + b1), owned outputs.
-    // The input [state | action] of row r is read as two segments.
-    {
-      const int O = d.Ha, n = O * Bc * ks1, kc = ceil_div(SA, ks1);
-      for (int e = tid; e < n; e += NT) {
-        const int o = e % O, r = (e / O) % Bc, qq = e / (O * Bc);
-        const int k0 = qq * kc, k1 = min(SA, k0 + kc);
-        float a = 0.f;
-        for (int k = k0; k < k1; ++k) {
-          float v;
-          if (k < S) v = sm[L.st + (size_t)r * S + k];
-          else if (L.preload) v = sm[L.act + ((size_t)t * Bc + r) * A + (k - S)];
-          else v = r < nr ? __ldg(p.actions + ((size_t)t * p.B + b0 + r) * A + (k - S)) : 0.f;
-          a = fmaf(sm[L.w1 + (size_t)k * O + o], v, a);
-        }
-        part1[((size_t)qq * Bc + r) * O + o] = a;
-      }
-      __syncthreads();
-      if (tr) p.trace[t * 16 + 10] = clock64();
-      for (int e = tid; e < ni * Bc; e += NT) {
-        const int o = e % ni, r = e / ni;
-        const float a = elu_f(part_sum(part1, O, Bc, ks1, r, o) + sm[L.b1 + o]);
+    float *bel_cur = sm + L.bel + (size_t)cur * Bc * RHp;
+    const size_t bel_nxt = L.bel + (size_t)(cur ^ 1) * Bc * RHp;
+    // ---- phase 1: a = ELU(W1 [state, action] + b1), owned outputs
+    for (int e = tid; e < Bc * SA; e += NT) {
+      const int r = e / SA, k = e % SA;
+      float v;
+      if (k < S) v = sm[L.st + (size_t)r * S + k];
+      else if (L.preload) v = sm[L.act + ((size_t)t * Bc + r) * A + (k - S)];
+      else v = r < nr ? __ldg(p.actions + ((size_t)t * p.B + b0 + r) * A + (k - S)) : 0.f;
+      sm[L.in1 + (size_t)r * SAp + k] = v;
+    }
+    __syncthreads();
+    matvec_part<NR>(sm + L.w1, d.Hap, SA, sm + L.in1, SAp, ks1, part1);
+    __syncthreads();
+    reduce_parts(part1, d.Hap, Bc, ks1);
+    __syncthreads();
+    if (tr) p.trace[t * 16 + 10] = clock64();
+    for (int e = tid; e < ni * Bc; e += NT) {
+      const int o = e % ni, r = e / ni;
+      const float a = elu_f(part_sum(part1, d.Hap, r, o) + sm[L.b1 + o]);
 #pragma unroll
-        for (int x = 0; x < RC; ++x) rem[x][L.av + (size_t)r * Hd + i0 + o] = a;
-      }
+      for (int x = 0; x < RC; ++x) rem[x][L.av + (size_t)r * Hdp + i0 + o] = a;
     }
     cluster.sync();
     if (tr) p.trace[t * 16 + 1] = globaltimer_ns();
     // ---- phase 2: GRUCell(a, belief) for owned units
     const long long c2 = clock64();
-    matvec_part<NR>(sm + L.wih, 3 * d.Ua, Hd, sm + L.av, Hd, ks2a, part1);
-    matvec_part<NR>(sm + L.whh, 3 * d.Ua, RH, bel_cur, RH, ks2b, part2);
+    matvec_part<NR>(sm + L.wih, d.U3p, Hd, sm + L.av, Hdp, ks2a, part1);
+    matvec_part<NR>(sm + L.whh, d.U3p, RH, bel_cur, RHp, ks2b, part2);
+    __syncthreads();
+    if (ks2a == ks2b) {
+      reduce_parts2(part1, part2, d.U3p, Bc, ks2a);
+    } else {
+      reduce_parts(part1, d.U3p, Bc, ks2a);
+      reduce_parts(part2, d.U3p, Bc, ks2b);
+    }
     __syncthreads();
     if (tr) p.trace[t * 16 + 8] = clock64() - c2;
     for (int e = tid; e < nj * Bc; e += NT) {
       const int j = e % nj, r = e / nj;
-      const int O = 3 * d.Ua;
+      const int O = d.U3p;
       float gi[3], gh[3];
 #pragma unroll
       for (int g = 0; g < 3; ++g) {
-        gi[g] = part_sum(part1, O, Bc, ks2a, r, g * d.Ua + j) + sm[L.bih + g * d.Ua + j];
-        gh[g] = part_sum(part2, O, Bc, ks2b, r, g * d.Ua + j) + sm[L.bhh + g * d.Ua + j];
+        gi[g] = part_sum(part1, O, r, g * d.Ua + j) + sm[L.bih + g * d.Ua + j];
+        gh[g] = part_sum(part2, O, r, g * d.Ua + j) + sm[L.bhh + g * d.Ua + j];
       }
       const float rg = sigmoid_f(gi[0] + gh[0]);
       const float zg = sigmoid_f(gi[1] + gh[1]);
       const float ng = tanh_f(gi[2] + rg * gh[2]);
-      const float hb = (1.f - zg) * ng + zg * bel_cur[(size_t)r * RH + j0 + j];
+      const float hb = (1.f - zg) * ng + zg * bel_cur[(size_t)r * RHp + j0 + j];
 #pragma unroll
-      for (int x = 0; x < RC; ++x) rem[x][bel_nxt + (size_t)r * RH + j0 + j] = hb;
+      for (int x = 0; x < RC; ++x) rem[x][bel_nxt + (size_t)r * RHp + j0 + j] = hb;
       if (r < nr) {
         float *dst = p.beliefs + ((size_t)t * p.B + b0 + r) * RH + j0 + j;
         if (e == tid) { out_v[0] = hb; out_p[0] = dst; }  // stored after the arrival
@@ -308,24 +367,28 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
     cl_wait();
     if (tr) p.trace[t * 16 + 2] = globaltimer_ns();
     // ---- phase 3: q = ELU(W2 belief + b2), owned outputs
-    matvec_part<NR>(sm + L.w2, d.Ha, RH, sm + bel_nxt, RH, ks3, part1);
+    matvec_part<NR>(sm + L.w2, d.Hap, RH, sm + bel_nxt, RHp, ks3, part1);
+    __syncthreads();
+    reduce_parts(part1, d.Hap, Bc, ks3);
     __syncthreads();
     for (int e = tid; e < ni * Bc; e += NT) {
       const int o = e % ni, r = e / ni;
-      const float qv = elu_f(part_sum(part1, d.Ha, Bc, ks3, r, o) + sm[L.b2 + o]);
+      const float qv = elu_f(part_sum(part1, d.Hap, r, o) + sm[L.b2 + o]);
 #pragma unroll
-      for (int x = 0; x < RC; ++x) rem[x][L.qv + (size_t)r * Hd + i0 + o] = qv;
+      for (int x = 0; x < RC; ++x) rem[x][L.qv + (size_t)r * Hdp + i0 + o] = qv;
     }
     cluster.sync();
     if (tr) p.trace[t * 16 + 3] = globaltimer_ns();
     // ---- phase 4: p = W3 q + b3 -> mean, std, sampled state (owned entries)
-    matvec_part<NR>(sm + L.w3, 2 * d.Sa, Hd, sm + L.qv, Hd, ks4, part1);
+    matvec_part<NR>(sm + L.w3, d.S2p, Hd, sm + L.qv, Hdp, ks4, part1);
+    __syncthreads();
+    reduce_parts(part1, d.S2p, Bc, ks4);
     __syncthreads();
     for (int e = tid; e < ns * Bc; e += NT) {
       const int j = e % ns, r = e / ns;
-      const float mean = part_sum(part1, 2 * d.Sa, Bc, ks4, r, j) + sm[L.b3 + j];
+      const float mean = part_sum(part1, d.S2p, r, j) + sm[L.b3 + j];
       const float sd =
-          softplus_f(part_sum(part1, 2 * d.Sa, Bc, ks4, r, d.Sa + j) + sm[L.b3 + d.Sa + j]) + 0.1f;
+          softplus_f(part_sum(part1, d.S2p, r, d.Sa + j) + sm[L.b3 + d.Sa + j]) + 0.1f;
       float st = mean;
       if (r < nr) {
         const size_t o = ((size_t)t * p.B + b0 + r) * S + s0 + j;
