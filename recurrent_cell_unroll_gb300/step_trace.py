@@ -1,0 +1,123 @@
+"""Per-step phase timings of the first layer's recurrent kernel.
+
+Runs one workload a few times, then once with the library's step trace on
+(RCU_ATTR_TRACE / rnn_get_trace, rssm_get_trace: CUDA global-timer stamps of
+CTA 0, resolution about 256 ns) and prints the median time between stamps.
+
+    python -m recurrent_cell_unroll_gb300.step_trace --workload gru --T 64 [--ksplit 1]
+
+Which stamps exist depends on the kernel that ran (named by the profile):
+tensor-core recurrence, portable SIMT recurrence, cluster-resident
+recurrence, or the RSSM unroll.  See include/rcu.h for the slot meanings.
+"""
+import argparse
+import sys
+
+import numpy as np
+import torch
+
+from . import binding
+from . import workloads as wl
+
+WORKLOADS = {"lstm": wl.LSTM_T80, "rssm": wl.RSSM_B50, "lstmp": wl.LSTMP_2L,
+             "bilstm": wl.BILSTM_VAR, "gru": wl.GRU_3L}
+
+# (from slot, to slot, label) per kernel
+PHASES = {
+    "recurrent_tc": [(0, 1, "step barrier seen -> first h stage landed"),
+                     (1, 8, "h stages streamed, MMAs issued"),
+                     (8, 3, "last stage -> epilogue has the accumulator"),
+                     (3, 5, "TMEM read (and partial sums sent)"),
+                     (5, 11, "partner's partial sums received"),
+                     (5, 6, "-> gates done, h_t stored"),
+                     (6, 4, "h_t published")],
+    "recurrent_simt": [(0, 3, "h_{t-1} rows loaded"), (3, 4, "mat-vec"),
+                       (4, 1, "gates, h_t stored"), (1, 2, "step barrier")],
+    "recurrent_cluster": [(0, 3, "mat-vec"), (3, 4, "gates"), (4, 1, "h_t sent")],
+    "rssm": [(0, 1, "Linear+ELU on [state, action]"), (1, 2, "GRUCell"),
+             (2, 3, "Linear+ELU"), (3, 4, "Linear, softplus, sample")],
+}
+
+
+def _medians(tr, phases):
+    out = []
+    for a, b, label in phases:
+        if not (np.any(tr[:, a]) and np.any(tr[:, b])):
+            continue
+        out.append((label, float(np.median(tr[:, b] - tr[:, a]))))
+    return out
+
+
+def run(workload: str, T: int = 0, ksplit: int = 0, seed: int = 0):
+    spec = WORKLOADS[workload]
+    if T > 0:
+        kw = {"T": T}
+        if getattr(spec, "varlen", None) is not None:
+            kw["varlen"] = (min(spec.varlen[0], T), T)
+        spec = spec.scaled(**kw)
+    dev = torch.device("cuda")
+    if isinstance(spec, wl.RssmSpec):
+        inp = wl.make_rssm_inputs(spec, seed=seed)
+        m = binding.RSSM(spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden)
+        m.set_weights(inp["weights"])
+        a, e = inp["actions"].to(dev), inp["eps"].to(dev)
+        for _ in range(3):
+            m.unroll(a, e)
+        binding.rssm_set_attr(m.h, binding.RCU_ATTR_TRACE, 1)
+        m.unroll(a, e)
+        tr = binding.rssm_get_trace(m.h, spec.T).numpy().astype(np.float64)
+        kernel = "rssm"
+    else:
+        inp = wl.make_rnn_inputs(spec, seed=seed)
+        net = binding.RNN.from_spec(spec)
+        if ksplit:
+            net.set_attr(binding.RCU_ATTR_TC_KSPLIT, ksplit)
+        net.set_weights(inp["weights"])
+        x = inp["x"].to(dev)
+        h0 = inp["h0"].to(dev) if inp["h0"] is not None else None
+        c0 = inp["c0"].to(dev) if inp["c0"] is not None else None
+        L = inp["lengths"].to(dev) if inp["lengths"] is not None else None
+        for _ in range(3):
+            net.forward(x, lengths=L, h0=h0, c0=c0)
+        net.set_attr(binding.RCU_ATTR_TRACE, 1)
+        net.set_attr(binding.RCU_ATTR_PROFILE, 1)
+        net.forward(x, lengths=L, h0=h0, c0=c0)
+        torch.cuda.synchronize()
+        if net.status() != 0:
+            raise RuntimeError("device status after the traced forward")
+        names = net.profile()
+        kernel = next((k for k in ("recurrent_tc", "recurrent_cluster", "recurrent_simt")
+                       if any(n.startswith(k) for n in names)), "recurrent_simt")
+        tr = binding.rnn_get_trace(net.h, spec.T).numpy().astype(np.float64)
+        net.close()
+    body = tr[2:max(3, spec.T - 1)]  # skip the first steps (cold) and the last
+    period = float(np.median(np.diff(body[:, 0]))) if len(body) > 1 else float("nan")
+    res = {"workload": spec.name, "T": spec.T, "kernel": kernel, "step_period_ns": period,
+           "phases_ns": _medians(body, PHASES[kernel])}
+    if kernel == "recurrent_tc" and np.any(body[:, 10]):
+        res["mma_thread_cycles"] = {"issuing": float(np.median(body[:, 10])),
+                                    "waiting": float(np.median(body[:, 9]))}
+        res["barrier_ns"] = float(np.median(body[1:, 0] - body[:-1, 4]))
+    return res
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--workload", default="gru", choices=sorted(WORKLOADS))
+    ap.add_argument("--T", type=int, default=64, help="sequence length (0 = the workload's)")
+    ap.add_argument("--ksplit", type=int, default=0, choices=[0, 1, 2])
+    args = ap.parse_args(argv)
+    r = run(args.workload, args.T, args.ksplit)
+    print(f"{r['workload']} T={r['T']} kernel={r['kernel']} "
+          f"step period (median) {r['step_period_ns']:.0f} ns")
+    for label, v in r["phases_ns"]:
+        print(f"  {label:45s} {v:8.0f} ns")
+    if "mma_thread_cycles" in r:
+        c = r["mma_thread_cycles"]
+        print(f"  MMA thread clock cycles: issuing {c['issuing']:.0f}, waiting {c['waiting']:.0f}")
+        print(f"  {'h_t published -> next step barrier seen':45s} {r['barrier_ns']:8.0f} ns")
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

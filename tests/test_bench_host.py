@@ -89,3 +89,18 @@ def test_reference_arm_prints_oracle_line(capsys, monkeypatch):
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0
     assert line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_step_trace_medians():
+    """Phase medians of the step-trace helper (host arithmetic only)."""
+    import numpy as np
+    from recurrent_cell_unroll_gb300 import step_trace
+    tr = np.zeros((5, 16))
+    tr[:, 0] = [0, 100, 200, 300, 400]
+    tr[:, 3] = tr[:, 0] + 10
+    tr[:, 4] = tr[:, 0] + 30
+    tr[:, 1] = tr[:, 0] + 60
+    got = dict(step_trace._medians(tr, step_trace.PHASES["recurrent_cluster"]))
+    assert got == {"mat-vec": 10.0, "gates": 20.0, "h_t sent": 30.0}
+    # phases whose stamps are absent are skipped
+    assert step_trace._medians(tr, [(5, 6, "absent")]) == []
