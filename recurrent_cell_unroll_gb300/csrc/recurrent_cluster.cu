@@ -112,7 +112,10 @@ __device__ __forceinline__ float4 wload(const __nv_bfloat16 *p) {
   return make_float4(a.x, a.y, b.x, b.y);
 }
 
-template <typename WT, int NG>
+// KQ4 > 0: the CTA's gate rows (at most 64) stay in registers, warp w owning
+// rows 4w..4w+3 over K = 128*KQ4 (lane l takes the 16-byte chunks l, l+32,
+// ...); KQ4 == 0: rows stay in shared memory, 8 lanes per row.
+template <typename WT, int NG, int KQ4>
 __global__ void __launch_bounds__(NT, 1)
     rec_cluster_kernel(const RecParams p, const void *W0, const void *W1, int U, int Kc, int Bc,
                        int NCL, int cs_plan) {
@@ -209,6 +212,18 @@ __global__ void __launch_bounds__(NT, 1)
   }
   prefetch(0);
 
+  // register-resident rows (KQ4 > 0): rows 4*warp + i, K chunks 4*lane + 128*m
+  float4 wreg[KQ4 > 0 ? 4 : 1][KQ4 > 0 ? KQ4 : 1];
+  if (KQ4 > 0) {
+#pragma unroll
+    for (int i = 0; i < (KQ4 > 0 ? 4 : 1); ++i) {
+      const int r = 4 * warp + i;
+#pragma unroll
+      for (int m = 0; m < (KQ4 > 0 ? KQ4 : 1); ++m)
+        wreg[i][m] = r < R ? wload(Ws + (size_t)r * Kc + 4 * lane + 128 * m)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
   int nact = nrow;  // active rows: the prefix of the slice with length > step
   int done = 0;     // steps whose input buffer completed
   for (int step = 0; step < Tcl; ++step) {
@@ -226,9 +241,39 @@ __global__ void __launch_bounds__(NT, 1)
     if (!s_ok) break;
     done = step + 1;
     if (tr) p.trace[step * 16 + 0] = globaltimer_ns();
-    // ---- h_{t-1} W_hh^T: a group of 8 lanes per output row (4 rows per warp
-    //      pass); lane l of a group takes the 16-byte K chunks l, l+8, ...
-    for (int b = 0; b < nact; ++b) {
+    // ---- h_{t-1} W_hh^T
+    if (KQ4 > 0) {
+      // 4 register rows per warp; the 4 lane-partial sums are reduced together
+      // (reduce-scatter: 2 + 1 shuffles leave lane l with row 2*bit4 + bit3,
+      // then 3 more within 8 lanes)
+      const bool hi16 = (lane & 16) != 0, hi8 = (lane & 8) != 0;
+      for (int b = 0; b < nact; ++b) {
+        const float *hrow = hcur + (size_t)b * Kc + 4 * lane;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < (KQ4 > 0 ? KQ4 : 1); ++m) {
+          const float4 x = *reinterpret_cast<const float4 *>(hrow + 128 * m);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            v[i] = fmaf(wreg[i][m].x, x.x, v[i]);
+            v[i] = fmaf(wreg[i][m].y, x.y, v[i]);
+            v[i] = fmaf(wreg[i][m].z, x.z, v[i]);
+            v[i] = fmaf(wreg[i][m].w, x.w, v[i]);
+          }
+        }
+        const float a0 = (hi16 ? v[2] : v[0]) + __shfl_xor_sync(0xffffffffu, hi16 ? v[0] : v[2], 16);
+        const float a1 = (hi16 ? v[3] : v[1]) + __shfl_xor_sync(0xffffffffu, hi16 ? v[1] : v[3], 16);
+        float a = (hi8 ? a1 : a0) + __shfl_xor_sync(0xffffffffu, hi8 ? a0 : a1, 8);
+        a += __shfl_xor_sync(0xffffffffu, a, 4);
+        a += __shfl_xor_sync(0xffffffffu, a, 2);
+        a += __shfl_xor_sync(0xffffffffu, a, 1);
+        const int r = 4 * warp + (hi16 ? 2 : 0) + (hi8 ? 1 : 0);
+        if ((lane & 7) == 0 && r < R) pre[(size_t)b * R + r] = a;
+      }
+    }
+    // 8 lanes per output row (4 rows per warp pass); lane l of a group takes
+    // the 16-byte K chunks l, l+8, ...
+    for (int b = 0; KQ4 == 0 && b < nact; ++b) {
       const float *hrow = hcur + (size_t)b * Kc + 4 * gl;
       for (int rw = warp * 4; rw < R; rw += NW * 4) {
         const int r = rw + grp;
@@ -303,9 +348,27 @@ __global__ void __launch_bounds__(NT, 1)
   }
 }
 
-template <typename WT>
-const void *cluster_kernel(int nG) {
-  return nG == 4 ? (const void *)rec_cluster_kernel<WT, 4> : (const void *)rec_cluster_kernel<WT, 3>;
+// register-resident rows when the CTA has at most 64 gate rows and K <= 512
+// (fp32 weights)
+int reg_kq4(int R, int Kc, bool wbf16) {
+  return (!wbf16 && R <= 4 * NW && Kc <= 512) ? Kc / 128 : 0;
+}
+
+template <int NG>
+const void *cluster_kernel_f32(int kq4) {
+  switch (kq4) {
+    case 1: return (const void *)rec_cluster_kernel<float, NG, 1>;
+    case 2: return (const void *)rec_cluster_kernel<float, NG, 2>;
+    case 3: return (const void *)rec_cluster_kernel<float, NG, 3>;
+    case 4: return (const void *)rec_cluster_kernel<float, NG, 4>;
+    default: return (const void *)rec_cluster_kernel<float, NG, 0>;
+  }
+}
+const void *cluster_kernel(int nG, bool wbf16, int kq4) {
+  if (wbf16)
+    return nG == 4 ? (const void *)rec_cluster_kernel<__nv_bfloat16, 4, 0>
+                   : (const void *)rec_cluster_kernel<__nv_bfloat16, 3, 0>;
+  return nG == 4 ? cluster_kernel_f32<4>(kq4) : cluster_kernel_f32<3>(kq4);
 }
 
 }  // namespace
@@ -334,9 +397,9 @@ bool plan_recurrent_cluster(ClusterRecPlan *cp, int cell, int H, int Hout, int T
                             bool wbf16, int max_rows) {
   const int nG = cell == CELL_LSTM ? 4 : 3, Kc = cluster_rec_kc(Hout);
   const size_t es = wbf16 ? 2 : 4;
-  const void *fn = wbf16 ? cluster_kernel<__nv_bfloat16>(nG) : cluster_kernel<float>(nG);
   for (int cs : {16, 8}) {
     const int U = ceil_div(H, cs);
+    const void *fn = cluster_kernel(nG, wbf16, reg_kq4(nG * U, Kc, wbf16));
     if (cs > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
                       cudaSuccess) {
       cudaGetLastError();
@@ -385,7 +448,7 @@ bool plan_recurrent_cluster(ClusterRecPlan *cp, int cell, int H, int Hout, int T
 
 cudaError_t launch_recurrent_cluster(const RecParams &p, const ClusterRecPlan &cp,
                                      const void *W0, const void *W1, bool wbf16, cudaStream_t s) {
-  const void *fn = wbf16 ? cluster_kernel<__nv_bfloat16>(p.nG) : cluster_kernel<float>(p.nG);
+  const void *fn = cluster_kernel(p.nG, wbf16, reg_kq4(p.nG * cp.U, cp.Kc, wbf16));
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)cp.smem);
   if (e != cudaSuccess) return e;

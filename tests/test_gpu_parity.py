@@ -316,6 +316,17 @@ def test_cluster_resident_kernel(spec):
     net.close()
 
 
+@pytest.mark.parametrize("in_dim", [64, 128, 256, 520])
+def test_input_projection_k_split(in_dim):
+    """fp32 input GEMM with few output tiles: K split over a 2/4/8-CTA cluster
+    (in_dim 64, 128, 256; 520 leaves the last slice short), partial tiles
+    summed over distributed shared memory."""
+    spec = wl.LSTM_T80.scaled(T=5, B=6, in_dim=in_dim, hidden=40, h0_std=0.3, c0_std=0.3)
+    inp = wl.make_rnn_inputs(spec, seed=23)
+    for path in (1, 3):
+        compare(spec, run_gpu(spec, inp, force_path=path), run_oracle(spec, inp))
+
+
 @pytest.mark.parametrize("ksplit", [1, 2])
 def test_barrier_timeout_on_tensor_core_path(ksplit):
     spec = wl.GRU_3L.scaled(layers=1, T=4, B=20, in_dim=16, hidden=128)
