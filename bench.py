@@ -375,6 +375,11 @@ def run_ours(args, spec, rank, local, ws):
         raise RuntimeError(f"device status {st} in the end-to-end loop")
 
     peaks = load_peaks()
+    extra = {}
+    if not isinstance(spec, wl.RssmSpec) and inp.get("lengths") is not None:
+        # varlen: also the rate of real (unpadded) row-steps
+        sum_len = int(inp["lengths"].sum())
+        extra["tokens_per_s"] = round(dist_sum(sum_len * args.steps, dev) / (max_ms / 1e3), 1)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 4),
@@ -392,6 +397,7 @@ def run_ours(args, spec, rank, local, ws):
         "gpu_launches": n_launch,
         "clocks": clk,
         "wall_s_timed_region": round(wall, 3),
+        **extra,
     }
     return line, inp
 
@@ -545,12 +551,17 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--T", type=int, default=0,
                     help="override the sequence length (small cases for profiler captures)")
+    ap.add_argument("--dtype", default="", choices=["", "f32", "bf16"],
+                    help="override the workload's weight type (bf16 on an fp32 workload is the "
+                         "opt-in down-conversion to the tensor cores)")
     ap.add_argument("--tc-ksplit", type=int, default=0, choices=[0, 1, 2],
                     help="tensor-core recurrence: CTAs splitting K (0 = the library's choice)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     spec = WORKLOADS[args.workload]
+    if args.dtype and not isinstance(spec, wl.RssmSpec) and args.dtype != spec.dtype:
+        spec = spec.scaled(dtype=args.dtype, name=f"{spec.name}@{args.dtype}")
     if args.T > 0:
         kw = {"T": args.T, "name": f"{spec.name}@T{args.T}"}
         if getattr(spec, "varlen", None) is not None:

@@ -56,7 +56,7 @@ def _load():
             i = ctypes.c_int
             lib.oracle_rnn_forward.restype = i
             lib.oracle_rnn_forward.argtypes = [i, i, i, i, i, i, i, i, i, P, P, P, P, P, P, P, P,
-                                               P, i, i]
+                                               P, i, i, P]
             lib.oracle_pack.restype = i
             lib.oracle_pack.argtypes = [i, i, P, P, P, P]
             lib.oracle_rssm_unroll.restype = i
@@ -116,8 +116,13 @@ def pack(lengths, T: int):
 
 def rnn_forward(cell: int, x, weights, *, hidden: int, proj: int = 0, bidirectional: bool = False,
                 lengths=None, h0=None, c0=None, bf16_weights: bool = False, rows=None,
-                threads: int = 0):
+                threads: int = 0, cell_clip=None, proj_clip=None):
     """Stacked LSTM / GRU (optionally bidirectional / projected) forward in fp64.
+
+    cell_clip / proj_clip: None or (lo, hi).  The LSTM cell state is clamped
+    to [lo, hi] as soon as it is updated (before tanh); the projected hidden
+    state as soon as it is formed (cell-state and projection clipping named in
+    "RNN Op Changes", apache/mxnet issue 9543).
 
     x: [T, B, in]; weights: list over layer*D + dir of dicts with keys
     w_ih, w_hh, b_ih, b_hh (None = zero) and w_hr (projection, LSTM only).
@@ -143,10 +148,16 @@ def rnn_forward(cell: int, x, weights, *, hidden: int, proj: int = 0, bidirectio
     hn = np.zeros((L * D, B, Hout), np.float64)
     cn = np.zeros((L * D, B, hidden), np.float64)
     rw = _i32(rows)
+    clip = None
+    if cell_clip is not None or proj_clip is not None:
+        inf = float("inf")
+        cl = cell_clip if cell_clip is not None else (-inf, inf)
+        pl = proj_clip if proj_clip is not None else (-inf, inf)
+        clip = np.array([cl[0], cl[1], pl[0], pl[1]], np.float64)
     rc = lib.oracle_rnn_forward(int(cell), int(bidirectional), L, in_dim, hidden, proj,
                                 int(bool(bf16_weights)), T, B, _ptr(x), _ptr(ln), _ptr(h0a),
                                 _ptr(c0a), ctypes.addressof(arr), _ptr(y), _ptr(hn), _ptr(cn),
-                                _ptr(rw), 0 if rw is None else len(rw), int(threads))
+                                _ptr(rw), 0 if rw is None else len(rw), int(threads), _ptr(clip))
     if rc != 0:
         raise ValueError("oracle_rnn_forward: invalid arguments")
     return y, hn, (cn if cell == LSTM else None)

@@ -121,11 +121,18 @@ int oracle_pack(int B, int T, const int32_t *lengths, int32_t *sorted_idx,
 /* in_seq: [len][in_w] input vectors of this row (time order);             */
 /* out:    [T][out_stride] written at column offset col for t < len.       */
 /* h, c:   state, updated in place (c unused for GRU).                     */
+/* clip: NULL, or {cell_lo, cell_hi, proj_lo, proj_hi}: the LSTM cell state
+   is clamped to [cell_lo, cell_hi] as soon as it is updated (before tanh),
+   the projected hidden state to [proj_lo, proj_hi] as soon as it is formed
+   (cell-state and projection clipping of cuDNN 7.2, "RNN Op Changes",
+   apache/mxnet issue 9543). */
+static double clampd(double v, double lo, double hi) { return v < lo ? lo : (v > hi ? hi : v); }
+
 static void run_direction(int cell, int in_w, int H, int P, int len, int reverse,
                           const double *in_seq, const double *Wih, const double *Whh,
                           const double *bih, const double *bhh, const double *Whr,
                           double *h, double *c, double *out, int out_stride, int col,
-                          double *scratch /* [nG*H + H] */) {
+                          double *scratch /* [nG*H + H] */, const double *clip) {
     const int nG = (cell == OR_LSTM) ? 4 : 3;
     const int Hout = P > 0 ? P : H;
     double *pre = scratch;          /* nG*H */
@@ -147,6 +154,7 @@ static void run_direction(int cell, int in_w, int H, int P, int len, int reverse
                 double gg = tanh(pre[2 * H + j]);
                 double og = sigmoid(pre[3 * H + j]);
                 c[j] = fg * c[j] + ig * gg;
+                if (clip) c[j] = clampd(c[j], clip[0], clip[1]);
                 m[j] = og * tanh(c[j]);
             }
             if (P > 0) {
@@ -154,7 +162,7 @@ static void run_direction(int cell, int in_w, int H, int P, int len, int reverse
                 for (int p = 0; p < P; ++p) {
                     double acc = 0.0;
                     for (int j = 0; j < H; ++j) acc += Whr[(size_t)p * H + j] * m[j];
-                    h[p] = acc;
+                    h[p] = clip ? clampd(acc, clip[2], clip[3]) : acc;
                 }
             } else {
                 for (int j = 0; j < H; ++j) h[j] = m[j];
@@ -205,7 +213,8 @@ static void run_direction(int cell, int in_w, int H, int P, int len, int reverse
 int oracle_rnn_forward(int cell, int bidir, int layers, int in_dim, int hidden, int proj,
                        int bf16_weights, int T, int B, const float *x, const int32_t *lengths,
                        const float *h0, const float *c0, const oracle_layer_w *w, double *y,
-                       double *h_n, double *c_n, const int32_t *rows, int nrows, int nthreads) {
+                       double *h_n, double *c_n, const int32_t *rows, int nrows, int nthreads,
+                       const double *clip) {
     if (cell != OR_LSTM && cell != OR_GRU) return -1;
     if (layers < 1 || in_dim < 1 || hidden < 1 || T < 0 || B < 0) return -1;
     if (proj < 0 || (proj > 0 && cell != OR_LSTM)) return -1;
@@ -267,7 +276,7 @@ int oracle_rnn_forward(int cell, int bidir, int layers, int in_dim, int hidden, 
                     for (int k = 0; k < H; ++k)
                         c[k] = c0 ? (double)c0[((size_t)i * B + b) * H + k] : 0.0;
                     run_direction(cell, in_w, H, P, len, d == 1, seq_a, Wih[i], Whh[i], bih[i],
-                                  bhh[i], Whr[i], h, c, seq_b, D * Hout, d * Hout, scratch);
+                                  bhh[i], Whr[i], h, c, seq_b, D * Hout, d * Hout, scratch, clip);
                     if (h_n)
                         for (int k = 0; k < Hout; ++k) h_n[((size_t)i * B + b) * Hout + k] = h[k];
                     if (c_n && cell == OR_LSTM)

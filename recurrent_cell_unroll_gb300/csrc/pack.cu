@@ -58,19 +58,29 @@ __global__ void __launch_bounds__(kMetaThreads) meta_kernel(const int32_t *__res
   const int t0 = tid * per, t1 = min(T, t0 + per);
   int sum = 0;
   for (int t = t0; t < t1; ++t) sum += m.batch_sizes[t];
-  s_part[tid] = sum;
+  // block-wide exclusive scan of the per-thread sums: inclusive scan inside
+  // each warp by shuffles, then of the warp totals by warp 0
+  const int lane = tid & 31, wid = tid >> 5, nw = (int)blockDim.x >> 5;
+  int inc = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  if (lane == 31) s_part[wid] = inc;
   __syncthreads();
-  if (tid == 0) {
-    int run = 0;
-    for (int i = 0; i < (int)blockDim.x; ++i) {
-      int v = s_part[i];
-      s_part[i] = run;
-      run += v;
+  if (wid == 0) {
+    int w = lane < nw ? s_part[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += v;
     }
-    m.step_off[T] = run;
+    if (lane < nw) s_part[lane] = w;  // inclusive warp totals
+    if (lane == nw - 1) m.step_off[T] = w;
   }
   __syncthreads();
-  int run = s_part[tid];
+  int run = inc - sum + (wid > 0 ? s_part[wid - 1] : 0);
   for (int t = t0; t < t1; ++t) {
     m.step_off[t] = run;
     run += m.batch_sizes[t];

@@ -327,6 +327,24 @@ def test_input_projection_k_split(in_dim):
         compare(spec, run_gpu(spec, inp, force_path=path), run_oracle(spec, inp))
 
 
+@pytest.mark.parametrize("spec", [
+    wl.LSTM_T80,
+    wl.BILSTM_VAR.scaled(T=40, B=16, in_dim=64, hidden=128, varlen=(5, 40)),
+], ids=lambda s: s.name)
+def test_opt_in_bf16_conversion_accuracy(spec):
+    """An fp32 workload run through the opt-in down-conversion (a bf16 handle:
+    weights and MMA operands rounded to bf16, fp32 state and accumulation),
+    against the exact fp32 model (the oracle with unrounded weights)."""
+    inp = wl.make_rnn_inputs(spec, seed=29)
+    got = run_gpu(spec.scaled(dtype="bf16"), inp)
+    ref = oracle.rnn_forward(_cell(spec), inp["x"], inp["weights"], hidden=spec.hidden,
+                             proj=spec.proj, bidirectional=spec.bidir, lengths=inp["lengths"],
+                             h0=inp["h0"], c0=inp["c0"], bf16_weights=False)
+    errs = {n: _rel(g, r) for n, g, r in zip(("y", "h_n", "c_n"), got, ref) if g is not None}
+    print(f"{spec.name}: relative error of the bf16 conversion vs the fp32 model {errs}")
+    assert all(e <= 3e-2 for e in errs.values()), errs
+
+
 @pytest.mark.parametrize("ksplit", [1, 2])
 def test_barrier_timeout_on_tensor_core_path(ksplit):
     spec = wl.GRU_3L.scaled(layers=1, T=4, B=20, in_dim=16, hidden=128)

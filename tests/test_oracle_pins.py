@@ -341,8 +341,9 @@ def test_batch_permutation_and_row_subset():
 
 # --------------------------------------------------------------------------- separately written scalar loops
 
-def _scalar_lstm(w, xs, h, c, proj):
-    """Independent scalar evaluation of one LSTM(P) direction over a list of steps."""
+def _scalar_lstm(w, xs, h, c, proj, cell_clip=None, proj_clip=None):
+    """Independent scalar evaluation of one LSTM(P) direction over a list of steps.
+    cell_clip / proj_clip: (lo, hi) bounds applied to c_t and to h_t = W_hr m_t."""
     H = len(c)
     out = []
     for xv in xs:
@@ -357,11 +358,15 @@ def _scalar_lstm(w, xs, h, c, proj):
         for j in range(H):
             ig, fg, gg, og = sg(row(j)), sg(row(H + j)), math.tanh(row(2 * H + j)), sg(row(3 * H + j))
             cj = fg * c[j] + ig * gg
+            if cell_clip is not None:
+                cj = min(max(cj, cell_clip[0]), cell_clip[1])
             newc.append(cj)
             m.append(og * math.tanh(cj))
         c = newc
         if proj:
             h = [sum(float(w["w_hr"][p][j]) * m[j] for j in range(H)) for p in range(proj)]
+            if proj_clip is not None:
+                h = [min(max(v, proj_clip[0]), proj_clip[1]) for v in h]
         else:
             h = m
         out.append(list(h))
@@ -409,6 +414,83 @@ def test_tiny_scalar_bruteforce(cell, proj):
             out, h = _scalar_gru(ws[0], xs, [float(v) for v in h0[0, b]])
         np.testing.assert_allclose(y[:, b], np.array(out), rtol=0, atol=1e-13)
         np.testing.assert_allclose(hn[0, b], h, rtol=0, atol=1e-13)
+
+
+# --------------------------------------------------------------------------- clipping
+# Cell-state and projection clipping (cuDNN 7.2 options discussed in "RNN Op
+# Changes", apache/mxnet issue 9543): c_t is clamped as soon as it is updated,
+# the projected h_t as soon as it is formed.
+
+@pytest.mark.parametrize("proj", [0, 2])
+def test_clipped_tiny_scalar_bruteforce(proj):
+    rng = np.random.default_rng(41 + proj)
+    T, B, I, H = 5, 3, 2, 3
+    ws = _rand_weights(rng, oracle.LSTM, 1, I, H, proj=proj, scale=1.5)
+    x = rng.standard_normal((T, B, I)).astype(np.float32)
+    Hout = proj or H
+    h0 = rng.standard_normal((1, B, Hout)).astype(np.float32)
+    c0 = rng.standard_normal((1, B, H)).astype(np.float32)
+    cc, pc = (-0.3, 0.4), ((-0.2, 0.25) if proj else None)
+    y, hn, cn = oracle.rnn_forward(oracle.LSTM, x, ws, hidden=H, proj=proj, h0=h0, c0=c0,
+                                   cell_clip=cc, proj_clip=pc)
+    y0, _, _ = oracle.rnn_forward(oracle.LSTM, x, ws, hidden=H, proj=proj, h0=h0, c0=c0)
+    assert np.abs(y - y0).max() > 1e-3  # the bounds are active
+    for b in range(B):
+        xs = [[float(v) for v in x[t, b]] for t in range(T)]
+        out, h, c = _scalar_lstm(ws[0], xs, [float(v) for v in h0[0, b]],
+                                 [float(v) for v in c0[0, b]], proj, cc, pc)
+        np.testing.assert_allclose(y[:, b], np.array(out), rtol=0, atol=1e-13)
+        np.testing.assert_allclose(hn[0, b], h, rtol=0, atol=1e-13)
+        np.testing.assert_allclose(cn[0, b], c, rtol=0, atol=1e-13)
+
+
+def test_cell_clip_saturated_closed_form():
+    """i = f = o = 1 (bias +40), W = 0: c_t = c_{t-1} + tanh(b_g) grows linearly,
+    so the clipped cell is clamp(t * tanh(b_g), lo, hi) and h_t = tanh(c_t)."""
+    H, T = 3, 8
+    ws = _zero_weights(oracle.LSTM, 1, 2, H)
+    bg = np.array([0.5, -0.5, 0.2], np.float32)
+    b = np.concatenate([np.full(H, 40, np.float32), np.full(H, 40, np.float32), bg,
+                        np.full(H, 40, np.float32)])
+    ws[0]["b_ih"] = b
+    x = np.zeros((T, 1, 2), np.float32)
+    lo, hi = -0.6, 0.9
+    y, hn, cn = oracle.rnn_forward(oracle.LSTM, x, ws, hidden=H, cell_clip=(lo, hi))
+    g = np.tanh(bg.astype(np.float64))
+    for t in range(T):
+        c = np.clip((t + 1) * g, lo, hi)
+        np.testing.assert_allclose(y[t, 0], np.tanh(c), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(cn[0, 0], np.clip(T * g, lo, hi), rtol=0, atol=1e-14)
+
+
+def test_proj_clip_closed_form():
+    """Same saturated cell with P = H and W_hr = 10 I: h_t = clamp(10 tanh(c_t), lo, hi)
+    and nothing feeds back (W_hh = 0)."""
+    H, T = 3, 6
+    ws = _zero_weights(oracle.LSTM, 1, 2, H, proj=H)
+    bg = np.array([0.05, -0.08, 0.02], np.float32)
+    ws[0]["b_ih"] = np.concatenate([np.full(H, 40, np.float32), np.full(H, 40, np.float32), bg,
+                                    np.full(H, 40, np.float32)])
+    ws[0]["w_hr"] = (10 * np.eye(H)).astype(np.float32)
+    x = np.zeros((T, 1, 2), np.float32)
+    lo, hi = -0.5, 0.7
+    y, hn, _ = oracle.rnn_forward(oracle.LSTM, x, ws, hidden=H, proj=H, proj_clip=(lo, hi))
+    g = np.tanh(bg.astype(np.float64))
+    for t in range(T):
+        np.testing.assert_allclose(y[t, 0], np.clip(10 * np.tanh((t + 1) * g), lo, hi),
+                                   rtol=0, atol=1e-13)
+
+
+def test_infinite_clip_equals_unclipped():
+    rng = np.random.default_rng(47)
+    ws = _rand_weights(rng, oracle.LSTM, 2, 3, 4, D=2, proj=2)
+    x = rng.standard_normal((6, 3, 3)).astype(np.float32)
+    inf = float("inf")
+    a = oracle.rnn_forward(oracle.LSTM, x, ws, hidden=4, proj=2, bidirectional=True)
+    b = oracle.rnn_forward(oracle.LSTM, x, ws, hidden=4, proj=2, bidirectional=True,
+                           cell_clip=(-inf, inf), proj_clip=(-inf, inf))
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
 
 
 # --------------------------------------------------------------------------- packing
