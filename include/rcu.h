@@ -89,6 +89,10 @@ typedef struct rcu_rssm_s *rcu_rssm_t;
                                          this handle launches (on the launching stream);
                                          read the totals with rnn_profile_entry */
 
+/* Clipping targets for rnn_set_clip. */
+#define RCU_CLIP_CELL 0 /* LSTM cell state c_t */
+#define RCU_CLIP_PROJ 1 /* projected hidden state h_t = W_hr m_t (LSTMP) */
+
 /* Message of the last failure on this host thread ("" if none). */
 RCU_API const char *rcu_last_error(void);
 
@@ -166,6 +170,20 @@ RCU_API int rnn_get_pack(rcu_rnn_t h, int32_t *sorted_idx, int32_t *unsorted_idx
 /* Synchronise `stream` and return the device status of the last forward
  * (RCU_OK, RCU_ERR_TIMEOUT or RCU_ERR_LENGTHS), then clear it. */
 RCU_API int rnn_get_status(rcu_rnn_t h, void *stream);
+
+/*
+ * Clipping of the LSTM state, the cell-state and projection clipping options
+ * of cuDNN 7.2 named in "RNN Op Changes" (apache/mxnet issue 9543):
+ *   RCU_CLIP_CELL: c_t = clamp(f*c_{t-1} + i*g, lo, hi), before tanh, so the
+ *                  clamped value feeds o*tanh(c_t), the next step and c_n;
+ *   RCU_CLIP_PROJ: h_t = clamp(W_hr m_t, lo, hi) (LSTMP), the value that feeds
+ *                  the next step, y and h_n.
+ * enable = 0 turns the target off (lo, hi ignored).  Bounds are used in fp32.
+ * Applies to every layer and direction from the next rnn_forward on.
+ * Errors: NULL handle, unknown target, lo > hi or NaN -> RCU_ERR_INVALID;
+ * GRU handle, or RCU_CLIP_PROJ without projection -> RCU_ERR_UNSUPPORTED.
+ */
+RCU_API int rnn_set_clip(rcu_rnn_t h, int what, int enable, double lo, double hi);
 
 /* Set a handle attribute (RCU_ATTR_*). */
 RCU_API int rnn_set_attr(rcu_rnn_t h, int attr, int64_t value);

@@ -28,10 +28,12 @@ RCU_OK, RCU_ERR_INVALID, RCU_ERR_UNSUPPORTED, RCU_ERR_CUDA = 0, -1, -2, -3
 RCU_ERR_TIMEOUT, RCU_ERR_LENGTHS, RCU_ERR_STATE = -4, -5, -6
 RCU_ATTR_BARRIER_TIMEOUT_NS, RCU_ATTR_TEST_DROP_ARRIVAL, RCU_ATTR_FORCE_PATH = 1, 2, 3
 RCU_ATTR_PROFILE, RCU_ATTR_TRACE, RCU_ATTR_TC_CLUSTER, RCU_ATTR_TC_KSPLIT = 4, 5, 6, 7
+RCU_CLIP_CELL, RCU_CLIP_PROJ = 0, 1
 
 EXPORTED = (
     "rcu_last_error", "rcu_version", "rnn_create", "rnn_set_weights", "rnn_forward",
-    "rnn_get_pack", "rnn_get_status", "rnn_set_attr", "rnn_last_launch_count", "rnn_destroy",
+    "rnn_get_pack", "rnn_get_status", "rnn_set_attr", "rnn_set_clip", "rnn_last_launch_count",
+    "rnn_destroy",
     "rnn_profile_entry", "rnn_profile_reset", "rnn_get_trace", "rnn_lstm_forward_noalloc",
     "rssm_create", "rssm_set_weights", "rssm_unroll", "rssm_get_status",
     "rssm_last_launch_count", "rssm_destroy", "rssm_set_attr", "rssm_get_trace",
@@ -72,6 +74,7 @@ def load(path: Optional[str] = None):
             "rnn_get_pack": (I, [P, P, P, P, P]),
             "rnn_get_status": (I, [P, P]),
             "rnn_set_attr": (I, [P, I, I64]),
+            "rnn_set_clip": (I, [P, I, I, ctypes.c_double, ctypes.c_double]),
             "rnn_last_launch_count": (I, [P]),
             "rnn_destroy": (I, [P]),
             "rnn_profile_entry": (I, [P, I, ctypes.POINTER(ctypes.c_char_p),
@@ -306,6 +309,14 @@ class RNN:
 
     def set_attr(self, attr, value):
         rnn_set_attr(self.h, attr, value)
+
+    def set_clip(self, what: int, bounds=None):
+        """Clamp the LSTM cell state (RCU_CLIP_CELL) or the projected hidden
+        state (RCU_CLIP_PROJ) to bounds = (lo, hi); None turns it off."""
+        if bounds is None:
+            _check(load().rnn_set_clip(self.h, what, 0, 0.0, 0.0))
+        else:
+            _check(load().rnn_set_clip(self.h, what, 1, float(bounds[0]), float(bounds[1])))
 
     def launch_count(self) -> int:
         return rnn_last_launch_count(self.h)

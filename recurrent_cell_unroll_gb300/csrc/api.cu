@@ -129,6 +129,9 @@ struct rcu_rnn_s {
   int force_path = 0;
   int tc_cluster = 0;  // CTAs per cluster sharing h loads in the tensor-core recurrent kernel
   int tc_ksplit = 0;   // CTAs splitting K in the tensor-core recurrent kernel (0 = automatic)
+  // LSTM clipping (rnn_set_clip)
+  int cclip = 0, pclip = 0;
+  float cclip_lo = 0.f, cclip_hi = 0.f, pclip_lo = 0.f, pclip_hi = 0.f;
   int launches = 0;
   bool used_tc_gemm = false, used_tc_rec = false;
   // opt-in per-step trace of the first layer's recurrent kernel
@@ -253,6 +256,28 @@ extern "C" int rnn_create(rcu_rnn_t *out, int cell, int layers, int in_dim, int 
   }
   cudaMemset(h->ctl.p, 0, ctl_bytes(layers));
   *out = h;
+  return RCU_OK;
+}
+
+extern "C" int rnn_set_clip(rcu_rnn_t h, int what, int enable, double lo, double hi) {
+  if (!h) return fail(RCU_ERR_INVALID, "rnn_set_clip: NULL handle");
+  if (what != RCU_CLIP_CELL && what != RCU_CLIP_PROJ)
+    return fail(RCU_ERR_INVALID, "rnn_set_clip: unknown target %d", what);
+  if (h->cell != RCU_LSTM)
+    return fail(RCU_ERR_UNSUPPORTED, "rnn_set_clip: clipping applies to LSTM cells");
+  if (what == RCU_CLIP_PROJ && h->P == 0)
+    return fail(RCU_ERR_UNSUPPORTED, "rnn_set_clip: projection clipping needs proj > 0");
+  if (enable && !(lo <= hi))  // also rejects NaN bounds
+    return fail(RCU_ERR_INVALID, "rnn_set_clip: need lo <= hi");
+  if (what == RCU_CLIP_CELL) {
+    h->cclip = enable != 0;
+    h->cclip_lo = (float)lo;
+    h->cclip_hi = (float)hi;
+  } else {
+    h->pclip = enable != 0;
+    h->pclip_lo = (float)lo;
+    h->pclip_hi = (float)hi;
+  }
   return RCU_OK;
 }
 
@@ -586,11 +611,19 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
     p.timeout_ns = (uint64_t)h->timeout_ns;
     p.drop_arrival = h->drop_arrival && l == 0;
     p.trace = (h->trace && l == 0) ? (unsigned long long *)h->trace_buf.p : nullptr;
+    p.cclip = h->cclip;
+    p.cclip_lo = h->cclip_lo;
+    p.cclip_hi = h->cclip_hi;
+    p.pclip = h->pclip;
+    p.pclip_lo = h->pclip_lo;
+    p.pclip_hi = h->pclip_hi;
 
     // ---- LSTMP on the tensor cores: recurrence on m with W_hh W_hr resident,
     //      then the projection of every step as one GEMM
     const int P = h->P, ldH = round_up(H, 8);
-    const bool folded = bf && P > 0 && !varlen && h->force_path != 1 && h->mbuf &&
+    // (a projection clip is applied to h_t before it feeds the next step, so
+    // the recurrence cannot be folded onto m)
+    const bool folded = bf && P > 0 && !varlen && !h->pclip && h->force_path != 1 && h->mbuf &&
                         h->lw[(size_t)l * D].fold_w.p && (H % 8) == 0 && ((D * H) % 8) == 0 &&
                         tc_rec_supported(RCU_LSTM, H, H, 0, h->nsm, B, D) &&
                         tc_gemm_supported(H, P);

@@ -70,6 +70,10 @@ struct RecParams {
   uint64_t timeout_ns;
   int drop_arrival;
   unsigned long long *trace;  // NULL, or [T][8] global-timer stamps written by CTA 0
+  // LSTM clipping: c_t clamped to [cclip_lo, cclip_hi] when updated (cclip != 0);
+  // projected h_t clamped to [pclip_lo, pclip_hi] when formed (pclip != 0)
+  int cclip, pclip;
+  float cclip_lo, cclip_hi, pclip_lo, pclip_hi;
 };
 // wbf16: weights stored bf16 (operands bf16) vs fp32.
 cudaError_t launch_recurrent_simt(const RecParams &p, bool wbf16, int nsm, cudaStream_t s);

@@ -308,6 +308,7 @@ __global__ void __launch_bounds__(NT, 1)
         const float gg = tanh_f(pr[2] + gx[2]);
         const float og = sigmoid_f(pr[3] + gx[3]);
         c = fg * c + ig * gg;
+        if (p.cclip) c = fminf(fmaxf(c, p.cclip_lo), p.cclip_hi);
         hv = og * tanh_f(c);
       } else {
         const float rg = sigmoid_f(gx[0] + pr[0]);

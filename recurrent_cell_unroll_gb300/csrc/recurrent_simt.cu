@@ -433,6 +433,7 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
           const float ig = sigmoid_f(ai), fg = sigmoid_f(af), gg = tanh_f(ag), og = sigmoid_f(ao);
           float c = cS[cidx(s, j)];
           c = fg * c + ig * gg;
+          if (p.cclip) c = fminf(fmaxf(c, p.cclip_lo), p.cclip_hi);
           cS[cidx(s, j)] = c;
           hv = og * tanh_f(c);
           if (proj) {
@@ -493,7 +494,8 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
             const int s = cb + i;
             const int tt = d == 0 ? step : lens[s] - 1 - step;
             const size_t row = (size_t)soff[tt] + s;
-            const float hv = red_sum(red, sp2.ks, CB, p.Pcp, i, j);
+            float hv = red_sum(red, sp2.ks, CB, p.Pcp, i, j);
+            if (p.pclip) hv = fminf(fmaxf(hv, p.pclip_lo), p.pclip_hi);
             hst_g[(size_t)s * Hout + q] = hv;
             hnxt[(size_t)s * Kp + q] = Op<WT>::from_f(hv);
             if (p.y) p.y[((size_t)tt * B + sidx[s]) * ldo + (size_t)d * Hout + q] = hv;

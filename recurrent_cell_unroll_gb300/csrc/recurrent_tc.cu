@@ -436,6 +436,7 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
             const float gg = tanh_fast(acc[2][j] + gx[2][j]);
             const float og = sigmoid_fast(acc[3][j] + gx[3][j]);
             c[j] = fg * c[j] + ig * gg;
+            if (p.cclip) c[j] = fminf(fmaxf(c[j], p.cclip_lo), p.cclip_hi);
             h[j] = og * tanh_fast(c[j]);
           } else {
             const float rg = sigmoid_fast(gx[0][j] + acc[0][j]);

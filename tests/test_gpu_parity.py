@@ -345,6 +345,71 @@ def test_opt_in_bf16_conversion_accuracy(spec):
     assert all(e <= 3e-2 for e in errs.values()), errs
 
 
+CLIP = [
+    # (spec, force_path, kernel expected in the profile, cell clip, projection clip)
+    (wl.LSTM_T80.scaled(T=12, B=9, in_dim=24, hidden=70, c0_std=0.5, h0_std=0.5), 3,
+     "recurrent_cluster", (-0.25, 0.3), None),
+    (wl.LSTM_T80.scaled(T=12, B=9, in_dim=24, hidden=70, c0_std=0.5, h0_std=0.5), 1,
+     "recurrent_simt", (-0.25, 0.3), None),
+    (wl.LSTMP_2L.scaled(dtype="f32", T=9, B=7, in_dim=17, hidden=52, proj=12), 1,
+     "recurrent_simt", (-0.2, 0.25), (-0.03, 0.04)),
+    (wl.LSTM_T80.scaled(name="lstm_bf16", dtype="bf16", T=12, B=150, in_dim=40, hidden=70,
+                        h0_std=0.5, c0_std=0.5), 2, "recurrent_tc", (-0.25, 0.3), None),
+    (wl.LSTMP_2L.scaled(T=9, B=130, in_dim=32, hidden=128, proj=64), 0,
+     "recurrent_tc_lstmp", (-0.2, 0.25), None),
+    (wl.LSTMP_2L.scaled(T=9, B=20, in_dim=32, hidden=128, proj=64), 0,
+     "recurrent_simt", (-0.2, 0.25), (-0.05, 0.06)),
+]
+
+
+@pytest.mark.parametrize("spec,path,kernel,cc,pc", CLIP,
+                         ids=lambda v: v.name if hasattr(v, "name") else None)
+def test_clipping_parity(spec, path, kernel, cc, pc):
+    """Cell-state / projection clipping on each recurrent kernel against the
+    clipped oracle; the bounds are active (the unclipped result differs)."""
+    inp = wl.make_rnn_inputs(spec, seed=31)
+    dev = torch.device("cuda")
+    net = binding.RNN.from_spec(spec)
+    if path:
+        net.set_attr(binding.RCU_ATTR_FORCE_PATH, path)
+    net.set_attr(binding.RCU_ATTR_PROFILE, 1)
+    net.set_weights(inp["weights"])
+    net.set_clip(binding.RCU_CLIP_CELL, cc)
+    if pc is not None:
+        net.set_clip(binding.RCU_CLIP_PROJ, pc)
+    h0 = inp["h0"].to(dev) if inp["h0"] is not None else None
+    c0 = inp["c0"].to(dev) if inp["c0"] is not None else None
+    y, hn, cn = net.forward(inp["x"].to(dev), h0=h0, c0=c0)
+    assert net.status() == 0
+    torch.cuda.synchronize()
+    assert kernel in net.profile()
+    ref = oracle.rnn_forward(_cell(spec), inp["x"], inp["weights"], hidden=spec.hidden,
+                             proj=spec.proj, h0=inp["h0"], c0=inp["c0"],
+                             bf16_weights=spec.dtype == "bf16", cell_clip=cc, proj_clip=pc)
+    unclipped = run_oracle(spec, inp)
+    # the bounds bite: the clipped output differs by over 5 % of its range
+    assert np.abs(ref[0] - unclipped[0]).max() > 0.05 * np.abs(unclipped[0]).max()
+    compare(spec, (y.cpu().numpy(), hn.cpu().numpy(), cn.cpu().numpy()), ref)
+    net.close()
+
+
+def test_clip_argument_errors():
+    gru = binding.RNN.from_spec(wl.GRU_3L.scaled(layers=1, T=2, B=2, in_dim=4, hidden=8))
+    with pytest.raises(binding.RcuError) as e:
+        gru.set_clip(binding.RCU_CLIP_CELL, (-1.0, 1.0))
+    assert e.value.code == binding.RCU_ERR_UNSUPPORTED
+    gru.close()
+    lstm = binding.RNN.from_spec(wl.LSTM_T80.scaled(T=2, B=2, in_dim=4, hidden=8))
+    with pytest.raises(binding.RcuError) as e:
+        lstm.set_clip(binding.RCU_CLIP_PROJ, (-1.0, 1.0))
+    assert e.value.code == binding.RCU_ERR_UNSUPPORTED
+    with pytest.raises(binding.RcuError) as e:
+        lstm.set_clip(binding.RCU_CLIP_CELL, (1.0, -1.0))
+    assert e.value.code == binding.RCU_ERR_INVALID
+    lstm.set_clip(binding.RCU_CLIP_CELL, None)  # off is always accepted
+    lstm.close()
+
+
 @pytest.mark.parametrize("ksplit", [1, 2])
 def test_barrier_timeout_on_tensor_core_path(ksplit):
     spec = wl.GRU_3L.scaled(layers=1, T=4, B=20, in_dim=16, hidden=128)
