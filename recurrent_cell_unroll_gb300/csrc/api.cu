@@ -684,16 +684,17 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
     }
 
     bool rec_done = false;
-    const bool tc_rec = bf && (h->force_path == 0 || h->force_path == 2) &&
-                        tc_rec_supported(h->cell, H, Hout, h->P, h->nsm, B, D) &&
-                        h->lw[(size_t)l * D].tc_whh.p;
-    // small problems: the cluster-resident kernel (automatic for slices of at
-    // most 16 rows per cluster)
+    // small problems first: the cluster-resident kernel (automatic when W_hh
+    // fits one cluster and the batch slices have at most 16 rows), else the
+    // tensor-core grid for bf16, else the SIMT grid
     ClusterRecPlan cp{};
-    const bool cl_rec = !tc_rec && (h->force_path == 0 || h->force_path == 3) &&
+    const bool cl_rec = (h->force_path == 0 || h->force_path == 3) &&
                         h->lw[(size_t)l * D].cl_whh.p &&
                         plan_recurrent_cluster(&cp, h->cell, H, Hout, T, B, D, bf,
                                                h->force_path == 3 ? (1 << 30) : 16);
+    const bool tc_rec = !cl_rec && bf && (h->force_path == 0 || h->force_path == 2) &&
+                        tc_rec_supported(h->cell, H, Hout, h->P, h->nsm, B, D) &&
+                        h->lw[(size_t)l * D].tc_whh.p;
     h->begin(tc_rec ? "recurrent_tc" : cl_rec ? "recurrent_cluster" : "recurrent_simt", s);
     if (tc_rec) {
       TcRecParams tp;

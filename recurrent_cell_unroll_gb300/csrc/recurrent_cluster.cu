@@ -349,27 +349,27 @@ __global__ void __launch_bounds__(NT, 1)
   }
 }
 
-// register-resident rows when the CTA has at most 64 gate rows and K <= 512
-// (fp32 weights)
+// register-resident rows (widened to fp32) when the CTA has at most 64 gate
+// rows and K <= 512
 int reg_kq4(int R, int Kc, bool wbf16) {
-  return (!wbf16 && R <= 4 * NW && Kc <= 512) ? Kc / 128 : 0;
+  (void)wbf16;
+  return (R <= 4 * NW && Kc <= 512) ? Kc / 128 : 0;
 }
 
-template <int NG>
-const void *cluster_kernel_f32(int kq4) {
+template <typename WT, int NG>
+const void *cluster_kernel_t(int kq4) {
   switch (kq4) {
-    case 1: return (const void *)rec_cluster_kernel<float, NG, 1>;
-    case 2: return (const void *)rec_cluster_kernel<float, NG, 2>;
-    case 3: return (const void *)rec_cluster_kernel<float, NG, 3>;
-    case 4: return (const void *)rec_cluster_kernel<float, NG, 4>;
-    default: return (const void *)rec_cluster_kernel<float, NG, 0>;
+    case 1: return (const void *)rec_cluster_kernel<WT, NG, 1>;
+    case 2: return (const void *)rec_cluster_kernel<WT, NG, 2>;
+    case 3: return (const void *)rec_cluster_kernel<WT, NG, 3>;
+    case 4: return (const void *)rec_cluster_kernel<WT, NG, 4>;
+    default: return (const void *)rec_cluster_kernel<WT, NG, 0>;
   }
 }
 const void *cluster_kernel(int nG, bool wbf16, int kq4) {
   if (wbf16)
-    return nG == 4 ? (const void *)rec_cluster_kernel<__nv_bfloat16, 4, 0>
-                   : (const void *)rec_cluster_kernel<__nv_bfloat16, 3, 0>;
-  return nG == 4 ? cluster_kernel_f32<4>(kq4) : cluster_kernel_f32<3>(kq4);
+    return nG == 4 ? cluster_kernel_t<__nv_bfloat16, 4>(kq4) : cluster_kernel_t<__nv_bfloat16, 3>(kq4);
+  return nG == 4 ? cluster_kernel_t<float, 4>(kq4) : cluster_kernel_t<float, 3>(kq4);
 }
 
 }  // namespace

@@ -416,6 +416,7 @@ def test_barrier_timeout_on_tensor_core_path(ksplit):
     inp = wl.make_rnn_inputs(spec, seed=14)
     dev = torch.device("cuda")
     net = binding.RNN.from_spec(spec)
+    net.set_attr(binding.RCU_ATTR_FORCE_PATH, 2)  # the grid-barrier kernel
     net.set_attr(binding.RCU_ATTR_TC_KSPLIT, ksplit)
     net.set_weights(inp["weights"])
     net.set_attr(binding.RCU_ATTR_BARRIER_TIMEOUT_NS, 50_000_000)
