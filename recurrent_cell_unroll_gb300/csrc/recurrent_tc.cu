@@ -372,7 +372,7 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
           }
         }
       }
-      // one thread waits for the accumulator; the verdict is shared so that
+      // one thread waits for the accumulator; its result is shared so that
       // all epilogue threads leave the loop together
       if (threadIdx.x == 64) ctl->go = tc::mbar_wait(&ctl->tfull, step & 1, p.err, abort, tmo);
       epi_bar();
