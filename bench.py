@@ -554,7 +554,7 @@ def main(argv=None):
     ap.add_argument("--dtype", default="", choices=["", "f32", "bf16"],
                     help="override the workload's weight type (bf16 on an fp32 workload is the "
                          "opt-in down-conversion to the tensor cores)")
-    ap.add_argument("--tc-ksplit", type=int, default=0, choices=[0, 1, 2],
+    ap.add_argument("--tc-ksplit", type=int, default=0, choices=[0, 1, 2, 4],
                     help="tensor-core recurrence: CTAs splitting K (0 = the library's choice)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

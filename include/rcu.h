@@ -84,7 +84,8 @@ typedef struct rcu_rssm_s *rcu_rssm_t;
                                          K (= hidden) dimension of h W_hh^T, exchanging
                                          partial sums through distributed shared memory
                                          (0 = automatic: 2 where it fits, 1 = no split,
-                                         2 = CTA pairs) */
+                                         2 = CTA pairs, 4 = clusters of 4; a split that
+                                         does not fit falls back to the next smaller) */
 #define RCU_ATTR_PROFILE 4            /* 1 = record a CUDA event pair around every kernel
                                          this handle launches (on the launching stream);
                                          read the totals with rnn_profile_entry */

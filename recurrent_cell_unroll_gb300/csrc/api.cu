@@ -298,7 +298,8 @@ extern "C" int rnn_set_attr(rcu_rnn_t h, int attr, int64_t value) {
       h->tc_cluster = (int)value;
       return RCU_OK;
     case RCU_ATTR_TC_KSPLIT:
-      if (value < 0 || value > 2) return fail(RCU_ERR_INVALID, "K split must be 0, 1 or 2");
+      if (value != 0 && value != 1 && value != 2 && value != 4)
+        return fail(RCU_ERR_INVALID, "K split must be 0, 1, 2 or 4");
       h->tc_ksplit = (int)value;
       return RCU_OK;
     case RCU_ATTR_TRACE:

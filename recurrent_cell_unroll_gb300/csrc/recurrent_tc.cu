@@ -108,7 +108,7 @@ __device__ __forceinline__ float sigmoid_fast(float x) { return fmaf(0.5f, tanh_
 
 template <int NG, int KS>
 __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p) {
-  static_assert(KS == 1 || KS == 2, "K is split over one or two CTAs");
+  static_assert(KS == 1 || KS == 2 || KS == 4, "K is split over 1, 2 or 4 CTAs");
   if (KS > 1 && tc::cluster_nctarank() != (uint32_t)KS) {
     // the K split needs its partner CTA: never address a peer that is not there
     if (threadIdx.x == 0) atomicCAS(p.err, DEV_OK, DEV_CONFIG);
@@ -139,15 +139,15 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   volatile int *abort = &ctl->abort;
   const uint64_t tmo = p.timeout_ns;
-  // Step barrier counters, one per K share of (d, bg): a CTA waits only for
-  // the CTAs that produce the h units of its own K blocks and arrives on the
-  // counter of the share its units fall in.  CTA c of (d, bg) finalises units
-  // [16c, 16c+16), and a K share boundary (nkbm*64) is a multiple of 16.
-  const int kbound = geo.nkbm * BK;
-  unsigned *ctr = p.ctr + (size_t)(d * NBG + bg) * KS + kr;
-  unsigned *ctr_arrive = p.ctr + (size_t)(d * NBG + bg) * KS + (KS > 1 && u0 >= kbound ? 1 : 0);
-  const int n_lo = KS > 1 ? min(NU, kbound / UNITS) : NU;  // CTAs arriving on share 0
-  const unsigned n_wait = (unsigned)(kr == 0 ? n_lo : NU - n_lo);
+  // One step-barrier counter per (d, bg), over all its CTAs.  Every CTA
+  // arrives only after it has consumed its peers' partial sums for the step,
+  // and a peer starts (and sends for) the next step only after the barrier:
+  // that ordering is what lets the partial-sum buffer be reused step after
+  // step and bounds the sends in flight to one step.  (Waiting only for the
+  // producers of a CTA's own K share would break it.)
+  unsigned *ctr = p.ctr + (size_t)(d * NBG + bg);
+  unsigned *ctr_arrive = ctr;
+  const unsigned n_wait = (unsigned)NU;
   // steps this batch group runs: the longest row of the group (rows sorted by length)
   const int Tg = row0 < B ? p.meta.lens_sorted[row0] : 0;
   // without a K split, an optional cluster of CTAs sharing (d, bg): each
@@ -321,13 +321,23 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
     // TMEM columns: [owner CTA][gate][16 units]; lane quarter q of the warp
     const uint32_t tl = tbase + ((uint32_t)(q * 32) << 16);
     const uint32_t own_col = (uint32_t)(kr * NG * UNITS + part * UPT);
-    const uint32_t peer_col = (uint32_t)((1 - kr) * NG * UNITS + part * UPT);  // KS == 2
-    // partial sums for the peer's units go to the same offset of its buffer:
-    // slot (g*4 + part)*128 + r, one float4 per (gate, thread)
-    uint32_t peer_x = 0, peer_bar = 0;
-    if (KS > 1) {
-      peer_x = tc::mapa_shared(tc::smem_u32(xbuf), (uint32_t)(1 - kr));
-      peer_bar = tc::mapa_shared(tc::smem_u32(&ctl->xfull), (uint32_t)(1 - kr));
+    // Peers i = 0..KS-2 are the other ranks in order.  The partial sums for
+    // peer pr's units go into pr's buffer, in the slot of this sender (its rank
+    // among pr's peers): slot*(NG*4*128) + (g*4 + part)*128 + r, one float4 per
+    // (gate, thread).
+    constexpr int NP = KS > 1 ? KS - 1 : 1;
+    constexpr int SLOT = NG * 4 * BG;  // float4 per slot
+    uint32_t peer_x[NP], peer_bar[NP], peer_col[NP];
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+      peer_x[i] = peer_bar[i] = peer_col[i] = 0;
+      if (KS > 1) {
+        const int pr = i < kr ? i : i + 1;
+        const int slot = kr < pr ? kr : kr - 1;
+        peer_x[i] = tc::mapa_shared(tc::smem_u32(xbuf + (size_t)slot * SLOT), (uint32_t)pr);
+        peer_bar[i] = tc::mapa_shared(tc::smem_u32(&ctl->xfull), (uint32_t)pr);
+        peer_col[i] = (uint32_t)(pr * NG * UNITS + part * UPT);
+      }
     }
     int x_posted = 0, x_done = 0;  // K split, thread 64: phases armed / completed
     float h[UPT], c[UPT], bn[UPT];
@@ -381,13 +391,15 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
       if (p.trace && blockIdx.x == 0 && threadIdx.x == 64) p.trace[step * 16 + 3] = globaltimer_ns();
       float acc[NG][UPT];
       {
-        uint32_t ra[NG][4], rp[KS > 1 ? NG : 1][4];
+        uint32_t ra[NG][4], rp[NP][KS > 1 ? NG : 1][4];
 #pragma unroll
         for (int g = 0; g < NG; ++g) tmem_ld4_nowait(tl + own_col + (uint32_t)(g * UNITS), ra[g]);
         if (KS > 1) {
 #pragma unroll
-          for (int g = 0; g < NG; ++g)
-            tmem_ld4_nowait(tl + peer_col + (uint32_t)(g * UNITS), rp[KS > 1 ? g : 0]);
+          for (int i = 0; i < NP; ++i)
+#pragma unroll
+            for (int g = 0; g < NG; ++g)
+              tmem_ld4_nowait(tl + peer_col[i] + (uint32_t)(g * UNITS), rp[i][KS > 1 ? g : 0]);
         }
         tmem_wait_ld();
         tc::tc_fence_before();
@@ -398,20 +410,23 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
 #pragma unroll
           for (int j = 0; j < UPT; ++j) acc[g][j] = __uint_as_float(ra[g][j]);
         if (KS > 1) {
-          // hand the peer its units' partial sums over K blocks [kb0, kb0+nk)
+          // hand each peer its units' partial sums over K blocks [kb0, kb0+nk)
 #pragma unroll
-          for (int g = 0; g < NG; ++g) {
-            const int gi = KS > 1 ? g : 0;
-            tc::st_async_v4(peer_x + (uint32_t)(((g * 4 + part) * BG + r) * 16),
-                            __uint_as_float(rp[gi][0]), __uint_as_float(rp[gi][1]),
-                            __uint_as_float(rp[gi][2]), __uint_as_float(rp[gi][3]), peer_bar);
-          }
+          for (int i = 0; i < NP; ++i)
+#pragma unroll
+            for (int g = 0; g < NG; ++g) {
+              const int gi = KS > 1 ? g : 0;
+              tc::st_async_v4(peer_x[i] + (uint32_t)(((g * 4 + part) * BG + r) * 16),
+                              __uint_as_float(rp[i][gi][0]), __uint_as_float(rp[i][gi][1]),
+                              __uint_as_float(rp[i][gi][2]), __uint_as_float(rp[i][gi][3]),
+                              peer_bar[i]);
+            }
           if (threadIdx.x == 64) ctl->x_sent = (uint32_t)(step + 1);
         }
       }
       if (p.trace && blockIdx.x == 0 && threadIdx.x == 64) p.trace[step * 16 + 5] = globaltimer_ns();
       if (KS > 1) {
-        // the peer's partial sums for this CTA's units
+        // the peers' partial sums for this CTA's units
         if (threadIdx.x == 64) {
           tc::mbar_arrive_expect_tx(&ctl->xfull, (uint32_t)geo.x_bytes);
           x_posted = step + 1;
@@ -421,10 +436,12 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
         epi_bar();
         if (!ctl->go2) break;
 #pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          const float4 v = xbuf[(g * 4 + part) * BG + r];
-          acc[g][0] += v.x; acc[g][1] += v.y; acc[g][2] += v.z; acc[g][3] += v.w;
-        }
+        for (int i = 0; i < NP; ++i)
+#pragma unroll
+          for (int g = 0; g < NG; ++g) {
+            const float4 v = xbuf[(size_t)i * SLOT + (g * 4 + part) * BG + r];
+            acc[g][0] += v.x; acc[g][1] += v.y; acc[g][2] += v.z; acc[g][3] += v.w;
+          }
         if (p.trace && blockIdx.x == 0 && threadIdx.x == 64) p.trace[step * 16 + 11] = globaltimer_ns();
       }
       if (active) {
@@ -503,13 +520,18 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
   // arrivals to it
   if (cs > 1 || KS > 1) tc::cluster_sync();
   if (KS > 1 && threadIdx.x == 64) {
-    // After an early exit the peer may have sent one step more than this CTA
+    // After an early exit a peer may have sent one step more than this CTA
     // consumed (never two: the peer's next step needs this CTA's arrival at
     // the step barrier, made only after consuming).  Those stores land in this
     // CTA's shared memory, so wait for them (bounded) before leaving.
     const int done = x_left < 0 ? -x_left - 1 : x_left;
-    const uint32_t peer_sent =
-        tc::ld_cluster_u32(tc::mapa_shared(tc::smem_u32(&ctl->x_sent), (uint32_t)(1 - kr)));
+    uint32_t peer_sent = 0;
+    for (int pr = 0; pr < KS; ++pr) {
+      if (pr == kr) continue;
+      const uint32_t v =
+          tc::ld_cluster_u32(tc::mapa_shared(tc::smem_u32(&ctl->x_sent), (uint32_t)pr));
+      peer_sent = v > peer_sent ? v : peer_sent;
+    }
     if ((int)peer_sent > done) {
       if (x_left >= 0) tc::mbar_arrive_expect_tx(&ctl->xfull, (uint32_t)geo.x_bytes);
       volatile int never = 0;
@@ -533,6 +555,13 @@ template <int NG>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT, 1)
     rec_tc_pair_kernel(const __grid_constant__ Maps maps, const RecParams p) {
   rec_tc_body<NG, 2>(maps, p);
+}
+// K split over 4 CTAs (GRU: the resident weights and the partial-sum buffer
+// fit beside a 3-stage h ring)
+template <int NG>
+__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(NT, 1)
+    rec_tc_quad_kernel(const __grid_constant__ Maps maps, const RecParams p) {
+  rec_tc_body<NG, 4>(maps, p);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -578,7 +607,7 @@ bool tc_rec_supported(int cell, int H, int Hout, int P, int nsm, int B, int D) {
   return ctas <= nsm;
 }
 
-int tc_rec_counters(int B, int D) { return 2 * D * ceil_div(B, BG); }
+int tc_rec_counters(int B, int D) { return D * ceil_div(B, BG); }
 
 void tc_pack_whh(int cell, int H, int Hout, const float *whh, std::vector<uint16_t> &out,
                  uint16_t (*to_bf16)(float)) {
@@ -599,7 +628,14 @@ namespace {
 
 template <int NG>
 const void *kernel_for(int ks) {
+  if (ks == 4) return (const void *)rec_tc_quad_kernel<NG>;
   return ks == 2 ? (const void *)rec_tc_pair_kernel<NG> : (const void *)rec_tc_kernel<NG>;
+}
+// a K split over ks CTAs fits: a ring of at least 2 h stages and a K block
+// for every CTA
+bool ks_fits(int nG, int K, int ks) {
+  const Geo g = make_geo(nG, K, ks);
+  return g.stages >= 2 && (ks - 1) * g.nkbm < g.nkb;
 }
 
 // Cooperative launch of `grid` CTAs in clusters of `cs`; false (nothing
@@ -656,17 +692,16 @@ cudaError_t launch_tc_recurrent(const TcRecParams &tp, int nsm, cudaStream_t s) 
   if (!make_map(&maps.hx, p.hx, (long long)p.D * 2 * p.B, p.Hout, p.Kp, BG))
     return cudaErrorInvalidValue;
 
-  // K split over a CTA pair: requested, or automatic when each CTA keeps at
-  // least one K block, the plan fits shared memory and no multicast cluster
-  // was asked for
+  // K split over ks CTAs (a cluster): requested (1, 2 or 4), or automatic (a
+  // pair) when no multicast cluster was asked for; halved until the plan fits
+  // shared memory and gives every CTA a K block
   int ks = tp.ksplit;
-  const bool ks2_ok = make_geo(nG, p.Hout, 2).stages >= 2 && make_geo(nG, p.Hout, 2).nkb >= 2;
-  if (ks == 0) ks = (ks2_ok && tp.cluster <= 1) ? 2 : 1;
-  if (ks == 2 && !ks2_ok) ks = 1;
+  if (ks == 0) ks = tp.cluster > 1 ? 1 : 2;
+  while (ks > 1 && !ks_fits(nG, p.Hout, ks)) ks /= 2;
 
-  for (int attempt = 0; attempt < 2; ++attempt) {
+  for (int attempt = 0; attempt < 3; ++attempt) {
     const Geo geo = make_geo(nG, p.Hout, ks);
-    p.NU = ks == 2 ? 2 * ceil_div(p.H, 2 * UNITS) : NU16;
+    p.NU = ks > 1 ? ks * ceil_div(p.H, ks * UNITS) : NU16;
     for (int d = 0; d < 2; ++d) {
       const void *w = tp.Wtc[d < p.D ? d : 0];
       if (!make_map(&maps.w[d], w, (long long)NU16 * nG * UNITS, p.Hout, p.Kp, geo.N))
@@ -678,9 +713,10 @@ cudaError_t launch_tc_recurrent(const TcRecParams &tp, int nsm, cudaStream_t s) 
     if (e != cudaSuccess) return e;
     const int grid = p.D * NBG * p.NU;
     void *args[] = {&maps, &p};
-    if (ks == 2) {
-      if (launch_clustered(fn, grid, 2, geo.smem, args, s, &e, true)) return e;
-      ks = 1;  // the pair grid cannot be co-resident: no split
+    if (ks > 1) {
+      if (launch_clustered(fn, grid, ks, geo.smem, args, s, &e, true)) return e;
+      ks /= 2;  // that cluster grid cannot be co-resident: a smaller split
+      while (ks > 1 && !ks_fits(nG, p.Hout, ks)) ks /= 2;
       continue;
     }
     // optional multicast cluster: the requested size, halved until it divides

@@ -105,7 +105,7 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--workload", default="gru", choices=sorted(WORKLOADS))
     ap.add_argument("--T", type=int, default=64, help="sequence length (0 = the workload's)")
-    ap.add_argument("--ksplit", type=int, default=0, choices=[0, 1, 2])
+    ap.add_argument("--ksplit", type=int, default=0, choices=[0, 1, 2, 4])
     args = ap.parse_args(argv)
     r = run(args.workload, args.T, args.ksplit)
     print(f"{r['workload']} T={r['T']} kernel={r['kernel']} "

@@ -256,7 +256,7 @@ KSPLIT = [
 
 
 @pytest.mark.parametrize("spec", KSPLIT, ids=lambda s: f"{s.name}-T{s.T}-B{s.B}-H{s.hidden}")
-@pytest.mark.parametrize("ksplit", [1, 2])
+@pytest.mark.parametrize("ksplit", [1, 2, 4])
 def test_tensor_core_k_split(spec, ksplit):
     """h W_hh^T with K kept whole (1) or split over a CTA pair (2) whose
     partial sums are exchanged through distributed shared memory."""
@@ -410,7 +410,7 @@ def test_clip_argument_errors():
     lstm.close()
 
 
-@pytest.mark.parametrize("ksplit", [1, 2])
+@pytest.mark.parametrize("ksplit", [1, 2, 4])
 def test_barrier_timeout_on_tensor_core_path(ksplit):
     spec = wl.GRU_3L.scaled(layers=1, T=4, B=20, in_dim=16, hidden=128)
     inp = wl.make_rnn_inputs(spec, seed=14)
