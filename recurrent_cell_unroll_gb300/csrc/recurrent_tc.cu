@@ -42,8 +42,13 @@ constexpr int SMEM_LIMIT = 227 * 1024;
 constexpr int MAX_STAGES = 8;
 
 struct Maps {
-  CUtensorMap hx;    // [D*2*B rows][K cols], ld Kp, bf16, box 64 x 128
+  CUtensorMap hx;    // [D*2*B rows][K cols], ld Kp, bf16, box 64 x a_rows
   CUtensorMap w[2];  // per direction [NU16*nG*16 rows][K cols], ld Kp, bf16, box 64 x N
+  // h rows loaded per stage: 128, or round_up(B, 8) when one batch group
+  // holds the whole batch (the stage's other rows are never read back: a
+  // row of D depends only on the same row of A, and the epilogue skips rows
+  // past B)
+  int a_rows;
 };
 
 struct Ctl {
@@ -220,7 +225,7 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
         for (int i = 0; i < nk; ++i) {
           const int kb = kb0 + i;
           if (!tc::mbar_wait(&ctl->empty[stage], phase ^ 1, p.err, abort, tmo)) goto producer_out;
-          tc::mbar_arrive_expect_tx(&ctl->full[stage], A_STAGE);
+          tc::mbar_arrive_expect_tx(&ctl->full[stage], (uint32_t)(maps.a_rows * BK * 2));
           if (cs == 1) {
             tc::tma_load_2d(sA + (size_t)stage * A_STAGE, &maps.hx, &ctl->full[stage], kb * BK,
                             arow);
@@ -689,7 +694,8 @@ cudaError_t launch_tc_recurrent(const TcRecParams &tp, int nsm, cudaStream_t s) 
   const int NU16 = ceil_div(p.H, UNITS);  // 16-unit tiles in the packed weights
   const int NBG = ceil_div(p.B, BG);
   Maps maps;
-  if (!make_map(&maps.hx, p.hx, (long long)p.D * 2 * p.B, p.Hout, p.Kp, BG))
+  maps.a_rows = NBG == 1 ? round_up(p.B, 8) : BG;
+  if (!make_map(&maps.hx, p.hx, (long long)p.D * 2 * p.B, p.Hout, p.Kp, maps.a_rows))
     return cudaErrorInvalidValue;
 
   // K split over ks CTAs (a cluster): requested (1, 2 or 4), or automatic (a
