@@ -90,9 +90,6 @@ __device__ __forceinline__ uint32_t cl_map_addr(uint32_t smem_addr, uint32_t ran
 __device__ __forceinline__ uint32_t cl_map(const void *p, uint32_t rank) {
   return cl_map_addr((uint32_t)__cvta_generic_to_shared(p), rank);
 }
-__device__ __forceinline__ void st_cl(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
 // 4-byte asynchronous store into a cluster CTA's shared memory, completing as
 // 4 bytes of complete_tx on that CTA's mbarrier
 __device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar) {
