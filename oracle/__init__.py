@@ -61,6 +61,9 @@ def _load():
             lib.oracle_pack.argtypes = [i, i, P, P, P, P]
             lib.oracle_rssm_unroll.restype = i
             lib.oracle_rssm_unroll.argtypes = [i, i, i, i, i, i] + [P] * 14 + [P, P, P, P, P, i, i]
+            lib.oracle_rssm_unroll2.restype = i
+            lib.oracle_rssm_unroll2.argtypes = ([i, i, i, i, i, i] + [P] * 14 + [P, P, P, P, P, i, i]
+                                                + [i, P, P, P, P, P])
             lib.oracle_bf16_round.restype = ctypes.c_double
             lib.oracle_bf16_round.argtypes = [ctypes.c_float]
             lib.oracle_num_threads_default.restype = i
@@ -190,3 +193,40 @@ def rssm_unroll(weights, actions, eps, *, state0=None, belief0=None, rows=None, 
     if rc != 0:
         raise ValueError("oracle_rssm_unroll: invalid arguments")
     return means, stds, states, beliefs
+
+
+def rssm_unroll_actor(weights, actor, eps, *, state0=None, belief0=None, rows=None,
+                      threads: int = 0):
+    """RSSM prior unroll with the actor in the loop (unroll variant 2) in fp64.
+
+    The action of step t is actor(state, belief) of the state and belief
+    before the step; actor = dict Wa1 [Ha, S+RH] (state columns first), ba1
+    [Ha], Wa2 [A, Ha], ba2 [A] (biases may be None), read as
+    action = tanh(Wa2 ELU(Wa1 [state, belief] + ba1) + ba2).  eps [T,B,S].
+    Returns (means, stds, states, beliefs, actions).
+    """
+    lib = _load()
+    e = _f32(eps)
+    T, B, S = e.shape
+    W = {k: _f32(v) for k, v in weights.items()}
+    Ac = {k: _f32(v) for k, v in actor.items()}
+    Hd = W["W1"].shape[0]
+    RH = W["W_hh"].shape[1]
+    A = Ac["Wa2"].shape[0]
+    Ha = Ac["Wa1"].shape[0]
+    means = np.zeros((T, B, S))
+    stds = np.zeros((T, B, S))
+    states = np.zeros((T, B, S))
+    beliefs = np.zeros((T, B, RH))
+    actions = np.zeros((T, B, A))
+    s0, b0 = _f32(state0), _f32(belief0)
+    rw = _i32(rows)
+    rc = lib.oracle_rssm_unroll2(S, A, Hd, RH, T, B, *[_ptr(W[k]) for k in (
+        "W1", "b1", "W_ih", "W_hh", "b_ih", "b_hh", "W2", "b2", "W3", "b3")],
+        _ptr(s0), _ptr(b0), None, _ptr(e), _ptr(means), _ptr(stds), _ptr(states),
+        _ptr(beliefs), _ptr(rw), 0 if rw is None else len(rw), int(threads), Ha,
+        _ptr(Ac["Wa1"]), _ptr(Ac.get("ba1")), _ptr(Ac["Wa2"]), _ptr(Ac.get("ba2")),
+        _ptr(actions))
+    if rc != 0:
+        raise ValueError("oracle_rssm_unroll_actor: invalid arguments")
+    return means, stds, states, beliefs, actions

@@ -326,14 +326,32 @@ int oracle_rnn_forward(int cell, int bidir, int layers, int in_dim, int hidden, 
 /* Whh [3RH, RH], W2 [Hd, RH], W3 [2S, Hd]; actions [T,B,A], eps [T,B,S],   */
 /* state0 [B,S], belief0 [B,RH] (NULL = zeros); means/stds/states [T,B,S],  */
 /* beliefs [T,B,RH].                                                        */
-int oracle_rssm_unroll(int S, int A, int Hd, int RH, int T, int B, const float *W1,
-                       const float *b1, const float *Wih, const float *Whh, const float *bih,
-                       const float *bhh, const float *W2, const float *b2, const float *W3,
-                       const float *b3, const float *state0, const float *belief0,
-                       const float *actions, const float *eps, double *means, double *stds,
-                       double *states, double *beliefs, const int32_t *rows, int nrows,
-                       int nthreads) {
+/*                                                                          */
+/* Unroll variant 2 ("Given an actor model, we unroll the states for H      */
+/* steps computing the actions on the fly", same page): the action of step  */
+/* t is actor(state, belief) of the state and belief before the step.  The  */
+/* page does not define the actor; it is read here as the plainest model    */
+/* in the style of the prior's own projectors, a deterministic two-layer    */
+/* MLP:  action = tanh(Wa2 ELU(Wa1 [state, belief] + ba1) + ba2),           */
+/* Wa1 [Ha, S+RH] (state columns first), ba1 [Ha], Wa2 [A, Ha], ba2 [A].    */
+/* actions_out [T,B,A] receives the actions used (may be NULL).            */
+/* With Wa1 == NULL, the actions are read from `actions` (variant 1).       */
+int oracle_rssm_unroll2(int S, int A, int Hd, int RH, int T, int B, const float *W1,
+                        const float *b1, const float *Wih, const float *Whh, const float *bih,
+                        const float *bhh, const float *W2, const float *b2, const float *W3,
+                        const float *b3, const float *state0, const float *belief0,
+                        const float *actions, const float *eps, double *means, double *stds,
+                        double *states, double *beliefs, const int32_t *rows, int nrows,
+                        int nthreads, int Ha, const float *Wa1, const float *ba1,
+                        const float *Wa2, const float *ba2, double *actions_out) {
     if (S < 1 || A < 0 || Hd < 1 || RH < 1 || T < 0 || B < 0) return -1;
+    const int actor = Wa1 != NULL;
+    if (actor && (Ha < 1 || !Wa2 || A < 1)) return -1;
+    if (!actor && A > 0 && !actions) return -1;
+    double *wa1 = actor ? widen(Wa1, (size_t)Ha * (S + RH), 0) : NULL;
+    double *vba1 = actor ? widen(ba1, Ha, 0) : NULL;
+    double *wa2 = actor ? widen(Wa2, (size_t)A * Ha, 0) : NULL;
+    double *vba2 = actor ? widen(ba2, A, 0) : NULL;
     const int nsel = rows ? nrows : B;
     double *w1 = widen(W1, (size_t)Hd * (S + A), 0), *vb1 = widen(b1, Hd, 0);
     double *wih = widen(Wih, (size_t)3 * RH * Hd, 0), *whh = widen(Whh, (size_t)3 * RH * RH, 0);
@@ -351,6 +369,8 @@ int oracle_rssm_unroll(int S, int A, int Hd, int RH, int T, int B, const float *
         double *a = (double *)malloc((size_t)Hd * sizeof(double));
         double *q = (double *)malloc((size_t)Hd * sizeof(double));
         double *p = (double *)malloc((size_t)2 * S * sizeof(double));
+        double *act = (double *)malloc((size_t)(A > 0 ? A : 1) * sizeof(double));
+        double *ha = (double *)malloc((size_t)(Ha > 0 ? Ha : 1) * sizeof(double));
 #ifdef _OPENMP
 #pragma omp for schedule(dynamic, 1)
 #endif
@@ -360,11 +380,29 @@ int oracle_rssm_unroll(int S, int A, int Hd, int RH, int T, int B, const float *
             for (int j = 0; j < RH; ++j)
                 bel[j] = belief0 ? (double)belief0[(size_t)b * RH + j] : 0.0;
             for (int t = 0; t < T; ++t) {
-                const float *act = actions + ((size_t)t * B + b) * A;
+                if (actor) {
+                    /* action = actor(state, belief), both before the step */
+                    for (int i = 0; i < Ha; ++i) {
+                        double u = vba1 ? vba1[i] : 0.0;
+                        for (int j = 0; j < S; ++j) u += wa1[(size_t)i * (S + RH) + j] * state[j];
+                        for (int j = 0; j < RH; ++j)
+                            u += wa1[(size_t)i * (S + RH) + S + j] * bel[j];
+                        ha[i] = elu(u);
+                    }
+                    for (int j = 0; j < A; ++j) {
+                        double v = vba2 ? vba2[j] : 0.0;
+                        for (int i = 0; i < Ha; ++i) v += wa2[(size_t)j * Ha + i] * ha[i];
+                        act[j] = tanh(v);
+                    }
+                } else {
+                    for (int j = 0; j < A; ++j) act[j] = (double)actions[((size_t)t * B + b) * A + j];
+                }
+                if (actions_out)
+                    for (int j = 0; j < A; ++j) actions_out[((size_t)t * B + b) * A + j] = act[j];
                 for (int i = 0; i < Hd; ++i) {
                     double u = vb1[i];
                     for (int j = 0; j < S; ++j) u += w1[(size_t)i * (S + A) + j] * state[j];
-                    for (int j = 0; j < A; ++j) u += w1[(size_t)i * (S + A) + S + j] * (double)act[j];
+                    for (int j = 0; j < A; ++j) u += w1[(size_t)i * (S + A) + S + j] * act[j];
                     a[i] = elu(u);
                 }
                 for (int j = 0; j < RH; ++j) {
@@ -413,10 +451,26 @@ int oracle_rssm_unroll(int S, int A, int Hd, int RH, int T, int B, const float *
         free(a);
         free(q);
         free(p);
+        free(act);
+        free(ha);
     }
     free(w1); free(vb1); free(wih); free(whh); free(vbih); free(vbhh);
     free(w2); free(vb2); free(w3); free(vb3);
+    free(wa1); free(vba1); free(wa2); free(vba2);
     return 0;
+}
+
+/* Unroll variant 1 (actions given). */
+int oracle_rssm_unroll(int S, int A, int Hd, int RH, int T, int B, const float *W1,
+                       const float *b1, const float *Wih, const float *Whh, const float *bih,
+                       const float *bhh, const float *W2, const float *b2, const float *W3,
+                       const float *b3, const float *state0, const float *belief0,
+                       const float *actions, const float *eps, double *means, double *stds,
+                       double *states, double *beliefs, const int32_t *rows, int nrows,
+                       int nthreads) {
+    return oracle_rssm_unroll2(S, A, Hd, RH, T, B, W1, b1, Wih, Whh, bih, bhh, W2, b2, W3, b3,
+                               state0, belief0, actions, eps, means, stds, states, beliefs, rows,
+                               nrows, nthreads, 0, NULL, NULL, NULL, NULL, NULL);
 }
 
 int oracle_num_threads_default(void) {

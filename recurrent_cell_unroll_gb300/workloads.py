@@ -142,3 +142,17 @@ def make_rssm_inputs(spec: RssmSpec, seed: int = 0) -> dict:
     if spec.belief0_std > 0:
         belief0 = torch.randn((spec.B, RH), generator=g, dtype=torch.float32) * spec.belief0_std
     return {"weights": w, "actions": actions, "eps": eps, "state0": state0, "belief0": belief0}
+
+
+def make_rssm_actor(spec: RssmSpec, seed: int = 0, actor_hidden: int = 0) -> dict:
+    """Weights of the actor of the second unroll variant (actions computed on
+    the fly): Wa1 [Ha, S+RH], ba1 [Ha], Wa2 [A, Ha], ba2 [A], U(+-1/sqrt(fan_in)),
+    Ha = spec.hidden unless given.  A separate generator (seed + 7919) leaves
+    make_rssm_inputs' draws unchanged."""
+    g = torch.Generator().manual_seed(seed + 7919)
+    S, A, RH = spec.state_dim, spec.action_dim, spec.rnn_hidden
+    Ha = actor_hidden or spec.hidden
+    b1 = 1.0 / math.sqrt(S + RH)
+    b2 = 1.0 / math.sqrt(Ha)
+    return {"Wa1": _uniform(g, (Ha, S + RH), b1), "ba1": _uniform(g, (Ha,), b1),
+            "Wa2": _uniform(g, (A, Ha), b2), "ba2": _uniform(g, (A,), b2)}

@@ -561,6 +561,73 @@ def _rssm_torch(w, actions, eps, state0, belief0):
     return [torch.stack([o[i] for o in outs]).numpy() for i in range(4)]
 
 
+def _rssm_actor_torch(w, actor, eps, state0, belief0):
+    """Unroll variant 2 from torch float64 modules: the actor (Linear, ELU,
+    Linear, Tanh on [state, belief]) picks each step's action."""
+    T, B, S = eps.shape
+    Hd = w["W1"].shape[0]
+    RH = w["W_hh"].shape[1]
+    A, Ha = actor["Wa2"].shape
+    d = lambda a: torch.from_numpy(np.asarray(a)).double()
+    lin1 = torch.nn.Linear(S + A, Hd, dtype=torch.float64)
+    gru = torch.nn.GRUCell(Hd, RH, dtype=torch.float64)
+    lin2 = torch.nn.Linear(RH, Hd, dtype=torch.float64)
+    lin3 = torch.nn.Linear(Hd, 2 * S, dtype=torch.float64)
+    act = torch.nn.Sequential(torch.nn.Linear(S + RH, Ha, dtype=torch.float64), torch.nn.ELU(),
+                              torch.nn.Linear(Ha, A, dtype=torch.float64), torch.nn.Tanh())
+    with torch.no_grad():
+        lin1.weight.copy_(d(w["W1"])); lin1.bias.copy_(d(w["b1"]))
+        gru.weight_ih.copy_(d(w["W_ih"])); gru.weight_hh.copy_(d(w["W_hh"]))
+        gru.bias_ih.copy_(d(w["b_ih"])); gru.bias_hh.copy_(d(w["b_hh"]))
+        lin2.weight.copy_(d(w["W2"])); lin2.bias.copy_(d(w["b2"]))
+        lin3.weight.copy_(d(w["W3"])); lin3.bias.copy_(d(w["b3"]))
+        act[0].weight.copy_(d(actor["Wa1"])); act[0].bias.copy_(d(actor["ba1"]))
+        act[2].weight.copy_(d(actor["Wa2"])); act[2].bias.copy_(d(actor["ba2"]))
+        state = torch.zeros(B, S, dtype=torch.float64) if state0 is None else d(state0)
+        belief = torch.zeros(B, RH, dtype=torch.float64) if belief0 is None else d(belief0)
+        outs = []
+        for t in range(T):
+            action = act(torch.cat([state, belief], dim=-1))
+            a = torch.nn.functional.elu(lin1(torch.cat([state, action], dim=-1)))
+            belief = gru(a, belief)
+            p = lin3(torch.nn.functional.elu(lin2(belief)))
+            mean, raw = p[:, :S], p[:, S:]
+            std = torch.nn.functional.softplus(raw) + 0.1
+            state = mean + d(eps[t]) * std
+            outs.append((mean, std, state, belief, action))
+    return [torch.stack([o[i] for o in outs]).numpy() for i in range(5)]
+
+
+def test_rssm_actor_against_torch_modules():
+    spec = wl.RSSM_B50.scaled(T=7, B=5, state_dim=5, action_dim=3, hidden=7, rnn_hidden=6,
+                              state0_std=0.5, belief0_std=0.5)
+    inp = wl.make_rssm_inputs(spec, seed=43)
+    actor = {k: v.numpy() for k, v in wl.make_rssm_actor(spec, seed=43, actor_hidden=4).items()}
+    got = oracle.rssm_unroll_actor(inp["weights"], actor, inp["eps"], state0=inp["state0"],
+                                   belief0=inp["belief0"])
+    ref = _rssm_actor_torch({k: v.numpy() for k, v in inp["weights"].items()}, actor,
+                            inp["eps"].numpy(), inp["state0"].numpy(), inp["belief0"].numpy())
+    for g, r in zip(got, ref):
+        np.testing.assert_allclose(g, r, rtol=0, atol=1e-12)
+
+
+def test_rssm_constant_actor_equals_given_actions():
+    """Zero actor weights with ba2 = atanh(v) act v at every step: the unroll
+    equals variant 1 with actions = v."""
+    spec = wl.RSSM_B50.scaled(T=6, B=3, state_dim=4, action_dim=2, hidden=5, rnn_hidden=6,
+                              belief0_std=0.5)
+    inp = wl.make_rssm_inputs(spec, seed=44)
+    v = np.array([0.3, -0.6], np.float32)
+    actor = {"Wa1": np.zeros((8, 10), np.float32), "ba1": np.ones(8, np.float32),
+             "Wa2": np.zeros((2, 8), np.float32), "ba2": np.arctanh(v.astype(np.float64)).astype(np.float32)}
+    got = oracle.rssm_unroll_actor(inp["weights"], actor, inp["eps"], belief0=inp["belief0"])
+    acts = np.broadcast_to(np.tanh(actor["ba2"].astype(np.float64)), (6, 3, 2)).astype(np.float32)
+    ref = oracle.rssm_unroll(inp["weights"], acts.copy(), inp["eps"], belief0=inp["belief0"])
+    for g, r in zip(got[:4], ref):
+        np.testing.assert_allclose(g, r, rtol=0, atol=1e-7)
+    np.testing.assert_allclose(got[4], acts, rtol=0, atol=1e-7)
+
+
 def test_rssm_against_torch_modules():
     spec = wl.RSSM_B50.scaled(T=6, B=4, state_dim=5, action_dim=3, hidden=7, rnn_hidden=6,
                               state0_std=1.0, belief0_std=0.5)
