@@ -35,7 +35,7 @@ from recurrent_cell_unroll_gb300 import workloads as wl  # noqa: E402
 
 WORKLOADS = {
     "lstm": wl.LSTM_T80, "rssm": wl.RSSM_B50, "lstmp": wl.LSTMP_2L,
-    "bilstm": wl.BILSTM_VAR, "gru": wl.GRU_3L,
+    "bilstm": wl.BILSTM_VAR, "gru": wl.GRU_3L, "rssm_actor": wl.RSSM_ACTOR,
 }
 METRIC = "(batch×timesteps)/s"
 UNIT = "(B·T)/s"
@@ -99,6 +99,8 @@ def kernel_flops(spec, inp) -> dict:
     if isinstance(spec, wl.RssmSpec):
         S, A, Hd, RH = spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden
         per = 2 * (Hd * (S + A) + 3 * RH * Hd + 3 * RH * RH + Hd * RH + 2 * S * Hd)
+        Hx = spec.actor_hidden
+        per += 2 * (Hx * (S + RH) + A * Hx)
         return {"rssm": [per * spec.B * spec.T]}
     M = active_rows(spec, inp)
     D, nG, H, Ho, P = spec.D, spec.nG, spec.hidden, spec.Hout, spec.proj
@@ -202,10 +204,16 @@ def make_runner(spec, inp, dev, tc_ksplit=0):
         T, B, S, RH = spec.T, spec.B, spec.state_dim, spec.rnn_hidden
         outs = [torch.empty((T, B, S), device=dev) for _ in range(3)] + \
             [torch.empty((T, B, RH), device=dev)]
+        if spec.actor_hidden:
+            m.set_actor(inp["actor"], device=dev)
+            outs.append(torch.empty((T, B, spec.action_dim), device=dev))
 
         def step():
-            binding.rssm_unroll(m.h, T, B, d["state0"], d["belief0"], d["actions"], d["eps"],
-                                *outs)
+            if spec.actor_hidden:
+                binding.rssm_unroll_actor(m.h, T, B, d["state0"], d["belief0"], d["eps"], *outs)
+            else:
+                binding.rssm_unroll(m.h, T, B, d["state0"], d["belief0"], d["actions"],
+                                    d["eps"], *outs)
 
         def launches():
             return binding.rssm_last_launch_count(m.h)
@@ -421,6 +429,9 @@ def compulsory_bytes(spec, inp) -> int:
     if isinstance(spec, wl.RssmSpec):
         S, A, Hd, RH = spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden
         w = Hd * (S + A + 1) + 3 * RH * (Hd + RH + 2) + Hd * (RH + 1) + 2 * S * (Hd + 1)
+        Hx = spec.actor_hidden
+        w += Hx * (S + RH + 1) + A * (Hx + 1)
+        # actions are read when given, written when the actor makes them
         io = spec.T * spec.B * (A + S + 3 * S + RH)
         return 4 * (w + io)
     es = 2 if spec.dtype == "bf16" else 4
@@ -443,7 +454,7 @@ def workload_config(spec, inp, ws):
          else "L2 flushed between timed steps (256 MB write)"}
     if isinstance(spec, wl.RssmSpec):
         c.update(state_dim=spec.state_dim, action_dim=spec.action_dim, hidden=spec.hidden,
-                 rnn_hidden=spec.rnn_hidden)
+                 rnn_hidden=spec.rnn_hidden, actor_hidden=spec.actor_hidden or None)
     else:
         c.update(cell=spec.cell, layers=spec.layers, in_dim=spec.in_dim, hidden=spec.hidden,
                  proj=spec.proj, bidirectional=spec.bidir,
@@ -455,7 +466,8 @@ def workload_config(spec, inp, ws):
 
 def input_bytes(spec, inp):
     if isinstance(spec, wl.RssmSpec):
-        return inp["actions"].numel() * 4 + inp["eps"].numel() * 4
+        a = inp["actions"].numel() * 4 if inp["actions"] is not None else 0
+        return a + inp["eps"].numel() * 4
     return inp["x"].numel() * 4
 
 
@@ -464,7 +476,10 @@ def input_bytes(spec, inp):
 def oracle_sample(spec, inp, rows, threads):
     import oracle
     t0 = time.perf_counter()
-    if isinstance(spec, wl.RssmSpec):
+    if isinstance(spec, wl.RssmSpec) and spec.actor_hidden:
+        oracle.rssm_unroll_actor(inp["weights"], inp["actor"], inp["eps"], state0=inp["state0"],
+                                 belief0=inp["belief0"], rows=rows, threads=threads)
+    elif isinstance(spec, wl.RssmSpec):
         oracle.rssm_unroll(inp["weights"], inp["actions"], inp["eps"], state0=inp["state0"],
                            belief0=inp["belief0"], rows=rows, threads=threads)
     else:

@@ -282,6 +282,30 @@ RCU_API int rssm_set_weights(rcu_rssm_t h, const float *W1, const float *b1, con
                      const float *b2, const float *W3, const float *b3, void *stream);
 
 /*
+ * RSSM unroll variant 2 ("Given an actor model, we unroll the states for H
+ * steps computing the actions on the fly", "[Feature Request] CUDNN version
+ * of RSSM", pytorch/rl issue 366, Solution).  The page leaves the actor
+ * undefined; it is taken as a deterministic two-layer MLP in the style of the
+ * prior's projectors:
+ *   action_t = tanh(Wa2 ELU(Wa1 [state_{t-1}, belief_{t-1}] + ba1) + ba2),
+ * evaluated on the state and belief before step t (state0/belief0 at t = 0).
+ * rssm_set_actor copies the actor (device fp32, row-major): Wa1
+ * [actor_hidden, state_dim + rnn_hidden] (state columns first), ba1
+ * [actor_hidden], Wa2 [action_dim, actor_hidden], ba2 [action_dim]; NULL bias
+ * = zero.  RCU_ERR_UNSUPPORTED if the actor does not fit beside the prior in
+ * one cluster's shared memory.
+ * rssm_unroll_actor: as rssm_unroll with T = the horizon and no actions
+ * input; actions_out [T,B,action_dim] receives the actions (may be NULL).
+ * RCU_ERR_STATE before rssm_set_actor.
+ */
+RCU_API int rssm_set_actor(rcu_rssm_t h, int actor_hidden, const float *Wa1, const float *ba1,
+                           const float *Wa2, const float *ba2, void *stream);
+RCU_API int rssm_unroll_actor(rcu_rssm_t h, int T, int B, const float *state0,
+                              const float *belief0, const float *eps, float *means,
+                              float *stds, float *states, float *beliefs, float *actions_out,
+                              void *stream);
+
+/*
  * Unroll T steps for B independent rows with given actions.  Per step:
  *   a = ELU(W1 [state, action_t] + b1); belief = GRUCell(a, belief);
  *   p = W3 ELU(W2 belief + b2) + b3; mean = p[:S]; std = softplus(p[S:]) + 0.1;
@@ -302,9 +326,10 @@ RCU_API int rssm_get_status(rcu_rssm_t h, void *stream);
 RCU_API int rssm_set_attr(rcu_rssm_t h, int attr, int64_t value);
 
 /*
- * Step trace of the last traced rssm_unroll: for each step t < n_steps, 16
- * stamps of CTA 0 copied to host_out[t*16 ..]: global timer (ns) at slots
- * 0 step start, 1 phase 1 done, 2 phase 2 done, 3 phase 3 done, 4 phase 4
+ * Step trace of the last traced rssm_unroll or rssm_unroll_actor: for each
+ * step t < n_steps, 16 stamps of CTA 0 copied to host_out[t*16 ..]: global
+ * timer (ns) at slots 0 step start, 5 actor done (rssm_unroll_actor only),
+ * 1 phase 1 done, 2 phase 2 done, 3 phase 3 done, 4 phase 4
  * done; SM clock cycles at 8 phase-2 mat-vec done, 9 phase-2 gates done,
  * 10 phase-1 partials done.  Synchronises the stream; host_out is host memory.
  */

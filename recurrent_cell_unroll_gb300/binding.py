@@ -37,6 +37,7 @@ EXPORTED = (
     "rnn_profile_entry", "rnn_profile_reset", "rnn_get_trace", "rnn_lstm_forward_noalloc",
     "rssm_create", "rssm_set_weights", "rssm_unroll", "rssm_get_status",
     "rssm_last_launch_count", "rssm_destroy", "rssm_set_attr", "rssm_get_trace",
+    "rssm_set_actor", "rssm_unroll_actor",
 )
 
 _lib = None
@@ -90,6 +91,8 @@ def load(path: Optional[str] = None):
             "rssm_destroy": (I, [P]),
             "rssm_set_attr": (I, [P, I, I64]),
             "rssm_get_trace": (I, [P, P, I, P]),
+            "rssm_set_actor": (I, [P, I, P, P, P, P, P]),
+            "rssm_unroll_actor": (I, [P, I, I] + [P] * 8 + [P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -243,6 +246,19 @@ def rssm_unroll(h, T: int, B: int, state0, belief0, actions, eps, means, stds, s
                               _stream(stream)))
 
 
+def rssm_set_actor(h, actor_hidden: int, Wa1, ba1, Wa2, ba2, stream=None):
+    keep = [_dev(t) for t in (Wa1, ba1, Wa2, ba2)]
+    _check(load().rssm_set_actor(h, actor_hidden, *[k[1] for k in keep], _stream(stream)))
+
+
+def rssm_unroll_actor(h, T: int, B: int, state0, belief0, eps, means, stds, states, beliefs,
+                      actions_out, stream=None):
+    ins = [_dev(t) for t in (state0, belief0, eps)]
+    outs = [_dev(t) for t in (means, stds, states, beliefs, actions_out)]
+    _check(load().rssm_unroll_actor(h, T, B, *[k[1] for k in ins], *[k[1] for k in outs],
+                                    _stream(stream)))
+
+
 def rssm_get_status(h, stream=None) -> int:
     return load().rssm_get_status(h, _stream(stream))
 
@@ -366,6 +382,28 @@ class RSSM:
         rssm_unroll(self.h, T, B, state0, belief0, actions, eps, means, stds, states, beliefs,
                     stream)
         return means, stds, states, beliefs
+
+    def set_actor(self, a, device="cuda", stream=None):
+        """Actor of the second unroll variant: dict Wa1 [Ha, S+RH], ba1 [Ha],
+        Wa2 [A, Ha], ba2 [A] (biases may be None)."""
+        t = {k: (None if v is None else v.to(device=device, dtype=torch.float32))
+             for k, v in a.items()}
+        rssm_set_actor(self.h, t["Wa1"].shape[0], t["Wa1"], t.get("ba1"), t["Wa2"],
+                       t.get("ba2"), stream)
+
+    def unroll_actor(self, eps, state0=None, belief0=None, stream=None):
+        """Unroll over eps' T steps with the actions computed by the actor;
+        returns (means, stds, states, beliefs, actions)."""
+        T, B, _ = eps.shape
+        dev = eps.device
+        means = torch.empty((T, B, self.S), device=dev)
+        stds = torch.empty_like(means)
+        states = torch.empty_like(means)
+        beliefs = torch.empty((T, B, self.RH), device=dev)
+        actions = torch.empty((T, B, self.A), device=dev)
+        rssm_unroll_actor(self.h, T, B, state0, belief0, eps, means, stds, states, beliefs,
+                          actions, stream)
+        return means, stds, states, beliefs, actions
 
     def launch_count(self) -> int:
         return rssm_last_launch_count(self.h)

@@ -811,6 +811,9 @@ struct rcu_rssm_s {
   int device, nsm;
   DevBuf W1, b1, Wih, Whh, bih, bhh, W2, b2, W3, b3;
   bool set = false;
+  // actor of unroll variant 2 (rssm_set_actor)
+  int Hx = 0;
+  DevBuf Wa1, ba1, Wa2, ba2;
   int launches = 0;
   DevBuf ctl;
   bool trace = false;
@@ -878,16 +881,43 @@ extern "C" int rssm_set_weights(rcu_rssm_t h, const float *W1, const float *b1, 
   return RCU_OK;
 }
 
-extern "C" int rssm_unroll(rcu_rssm_t h, int T, int B, const float *state0, const float *belief0,
-                           const float *actions, const float *eps, float *means, float *stds,
-                           float *states, float *beliefs, void *stream) {
-  if (!h) return fail(RCU_ERR_INVALID, "rssm_unroll: NULL handle");
+extern "C" int rssm_set_actor(rcu_rssm_t h, int actor_hidden, const float *Wa1, const float *ba1,
+                              const float *Wa2, const float *ba2, void *stream) {
+  if (!h) return fail(RCU_ERR_INVALID, "rssm_set_actor: NULL handle");
+  if (actor_hidden < 1 || !Wa1 || !Wa2 || h->A < 1)
+    return fail(RCU_ERR_INVALID, "rssm_set_actor: need actor_hidden >= 1, Wa1, Wa2, action_dim >= 1");
+  if (!rssm_supported(h->S, h->A, h->Hd, h->RH, actor_hidden))
+    return fail(RCU_ERR_UNSUPPORTED, "rssm_set_actor: weights do not fit one cluster's shared memory");
+  cudaStream_t s = (cudaStream_t)stream;
+  const int S = h->S, A = h->A, RH = h->RH, Hx = actor_hidden;
+  struct Item { DevBuf *dst; const float *src; size_t n; };
+  Item items[] = {{&h->Wa1, Wa1, (size_t)Hx * (S + RH)}, {&h->ba1, ba1, (size_t)Hx},
+                  {&h->Wa2, Wa2, (size_t)A * Hx}, {&h->ba2, ba2, (size_t)A}};
+  for (auto &it : items) {
+    CU(it.dst->ensure(std::max<size_t>(it.n, 1) * 4));
+    if (it.src)
+      CU(cudaMemcpyAsync(it.dst->p, it.src, it.n * 4, cudaMemcpyDeviceToDevice, s));
+    else
+      CU(cudaMemsetAsync(it.dst->p, 0, it.n * 4, s));
+  }
+  CU(cudaStreamSynchronize(s));
+  h->Hx = Hx;
+  return RCU_OK;
+}
+
+static int rssm_run(rcu_rssm_t h, bool with_actor, int T, int B, const float *state0,
+                    const float *belief0, const float *actions, const float *eps, float *means,
+                    float *stds, float *states, float *beliefs, float *actions_out, void *stream) {
+  const char *fn = with_actor ? "rssm_unroll_actor" : "rssm_unroll";
+  if (!h) return fail(RCU_ERR_INVALID, "%s: NULL handle", fn);
   h->launches = 0;
-  if (!h->set) return fail(RCU_ERR_STATE, "rssm_unroll: weights not set");
-  if (T < 0 || B < 0) return fail(RCU_ERR_INVALID, "rssm_unroll: T and B must be >= 0");
+  if (!h->set) return fail(RCU_ERR_STATE, "%s: weights not set", fn);
+  if (with_actor && h->Hx < 1) return fail(RCU_ERR_STATE, "%s: actor not set", fn);
+  if (T < 0 || B < 0) return fail(RCU_ERR_INVALID, "%s: T and B must be >= 0", fn);
   if (T == 0 || B == 0) return RCU_OK;
-  if ((h->A > 0 && !actions) || !eps || !means || !stds || !states || !beliefs)
-    return fail(RCU_ERR_INVALID, "rssm_unroll: actions, eps and all outputs are required");
+  if ((!with_actor && h->A > 0 && !actions) || !eps || !means || !stds || !states || !beliefs)
+    return fail(RCU_ERR_INVALID, "%s: actions (without an actor), eps and all outputs are required",
+                fn);
   RssmParams p{};
   p.S = h->S; p.A = h->A; p.Hd = h->Hd; p.RH = h->RH; p.T = T; p.B = B;
   p.W1 = (const float *)h->W1.p; p.b1 = (const float *)h->b1.p;
@@ -897,6 +927,13 @@ extern "C" int rssm_unroll(rcu_rssm_t h, int T, int B, const float *state0, cons
   p.W3 = (const float *)h->W3.p; p.b3 = (const float *)h->b3.p;
   p.state0 = state0; p.belief0 = belief0; p.actions = actions; p.eps = eps;
   p.means = means; p.stds = stds; p.states = states; p.beliefs = beliefs;
+  if (with_actor) {
+    p.actions = nullptr;
+    p.Hx = h->Hx;
+    p.Wa1 = (const float *)h->Wa1.p; p.ba1 = (const float *)h->ba1.p;
+    p.Wa2 = (const float *)h->Wa2.p; p.ba2 = (const float *)h->ba2.p;
+    p.actions_out = actions_out;
+  }
   p.trace = nullptr;
   if (h->trace) {
     CU(h->trace_buf.ensure((size_t)T * 16 * 8));
@@ -909,6 +946,20 @@ extern "C" int rssm_unroll(rcu_rssm_t h, int T, int B, const float *state0, cons
   if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rssm kernel launch: %s", cudaGetErrorString(e));
   h->launches = 1;
   return RCU_OK;
+}
+
+extern "C" int rssm_unroll(rcu_rssm_t h, int T, int B, const float *state0, const float *belief0,
+                           const float *actions, const float *eps, float *means, float *stds,
+                           float *states, float *beliefs, void *stream) {
+  return rssm_run(h, false, T, B, state0, belief0, actions, eps, means, stds, states, beliefs,
+                  nullptr, stream);
+}
+
+extern "C" int rssm_unroll_actor(rcu_rssm_t h, int T, int B, const float *state0,
+                                 const float *belief0, const float *eps, float *means, float *stds,
+                                 float *states, float *beliefs, float *actions_out, void *stream) {
+  return rssm_run(h, true, T, B, state0, belief0, nullptr, eps, means, stds, states, beliefs,
+                  actions_out, stream);
 }
 
 extern "C" int rssm_get_status(rcu_rssm_t h, void *stream) {

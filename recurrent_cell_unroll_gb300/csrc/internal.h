@@ -112,8 +112,15 @@ struct RssmParams {
   const float *state0, *belief0, *actions, *eps;
   float *means, *stds, *states, *beliefs;
   unsigned long long *trace;  // NULL, or [T][16] stamps written by CTA 0 (see rssm_get_trace)
+  // unroll variant 2: Wa1 != NULL computes each step's action as
+  // tanh(Wa2 ELU(Wa1 [state, belief] + ba1) + ba2) (Wa1 [Hx, S+RH], Wa2 [A, Hx]);
+  // actions_out [T,B,A] receives them (may be NULL); `actions` is unused
+  int Hx;
+  const float *Wa1, *ba1, *Wa2, *ba2;
+  float *actions_out;
 };
 cudaError_t launch_rssm(const RssmParams &p, int nsm, cudaStream_t s, int *clusters_used);
-bool rssm_supported(int S, int A, int Hd, int RH);
+// the weights (and, with Hx > 0, the actor's) fit one cluster's shared memory
+bool rssm_supported(int S, int A, int Hd, int RH, int Hx = 0);
 
 }  // namespace rcu

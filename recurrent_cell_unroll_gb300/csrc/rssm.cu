@@ -34,6 +34,7 @@ constexpr int NT = 512;
 constexpr int MAXBC = 8; // batch rows per cluster
 constexpr int KS_MAX = 16;
 constexpr size_t PRELOAD_MAX = 32 * 1024;  // bytes of actions+eps kept in shared memory
+constexpr size_t SMEM_CAP = 227 * 1024;    // dynamic shared memory per CTA
 
 __host__ __device__ inline int r4(int v) { return (v + 3) & ~3; }
 
@@ -41,9 +42,12 @@ struct Dims {
   int S, A, Hd, RH, Ha, Ua, Sa, Bc;
   // padded widths (multiples of 4 floats, so rows start 16-byte aligned)
   int Hap, U3p, S2p, Hdp, RHp, SAp;
+  // actor in the loop (Hx = actor hidden width, 0 = none): outputs per CTA
+  // and padded widths
+  int Hx, Hxa, Axa, Hxap, Axap, Hxp, SRp;
 };
 
-__host__ __device__ inline Dims make_dims(int S, int A, int Hd, int RH, int Bc) {
+__host__ __device__ inline Dims make_dims(int S, int A, int Hd, int RH, int Bc, int Hx = 0) {
   Dims d;
   d.S = S; d.A = A; d.Hd = Hd; d.RH = RH;
   d.Ha = ceil_div(Hd, RC);
@@ -56,6 +60,13 @@ __host__ __device__ inline Dims make_dims(int S, int A, int Hd, int RH, int Bc) 
   d.Hdp = r4(Hd);
   d.RHp = r4(RH);
   d.SAp = r4(S + A);
+  d.Hx = Hx;
+  d.Hxa = Hx > 0 ? ceil_div(Hx, RC) : 0;
+  d.Axa = Hx > 0 ? ceil_div(A, RC) : 0;
+  d.Hxap = r4(d.Hxa);
+  d.Axap = r4(d.Axa);
+  d.Hxp = r4(Hx);
+  d.SRp = Hx > 0 ? r4(S + RH) : 0;
   return d;
 }
 
@@ -71,7 +82,9 @@ __host__ __device__ inline int split_of(int Op, int K) {
 // shared-memory carve-up (floats)
 struct Layout {
   size_t w1, b1, wih, whh, bih, bhh, w2, b2, w3, b3;  // weights (transposed [k][o], o padded)
+  size_t wa1, ba1, wa2, ba2;                           // actor weights (same form)
   size_t st, in1, av, bel, qv;                         // vectors, [Bc][padded width]
+  size_t ain, hx;                                      // actor input [state, belief], hidden
   size_t part1, part2;                                 // chunk partials
   size_t act, eps;                                     // preloaded actions / noise
   size_t total;
@@ -91,19 +104,39 @@ __host__ __device__ inline Layout make_layout(const Dims &d, int T) {
   L.b2 = take(d.Hap);
   L.w3 = take((size_t)d.Hd * d.S2p);
   L.b3 = take(d.S2p);
+  L.wa1 = take(d.Hx > 0 ? (size_t)(d.S + d.RH) * d.Hxap : 0);
+  L.ba1 = take(d.Hx > 0 ? d.Hxap : 0);
+  L.wa2 = take(d.Hx > 0 ? (size_t)d.Hx * d.Axap : 0);
+  L.ba2 = take(d.Hx > 0 ? d.Axap : 0);
   L.st = take((size_t)d.Bc * d.S);
   L.in1 = take((size_t)d.Bc * d.SAp);
+  // a (phase 1 -> 2) and q (phase 3 -> 4) share storage: peers write q only
+  // after the cluster barrier that ends phase 2, when every CTA has read a,
+  // and write a only after the step's last barrier, when q has been read
   L.av = take((size_t)d.Bc * d.Hdp);
+  L.qv = L.av;
   L.bel = take((size_t)2 * d.Bc * d.RHp);
-  L.qv = take((size_t)d.Bc * d.Hdp);
   int wmax = d.Hap > d.U3p ? d.Hap : d.U3p;
   if (d.S2p > wmax) wmax = d.S2p;
+  if (d.Hxap > wmax) wmax = d.Hxap;
+  if (d.Axap > wmax) wmax = d.Axap;
   L.part1 = take((size_t)KS_MAX * d.Bc * wmax);
-  L.part2 = take((size_t)KS_MAX * d.Bc * d.U3p);
-  const size_t pre = (size_t)T * d.Bc * (d.A + d.S);
-  L.preload = pre * 4 <= PRELOAD_MAX;
-  L.act = take(L.preload ? (size_t)T * d.Bc * d.A : 0);
-  L.eps = take(L.preload ? (size_t)T * d.Bc * d.S : 0);
+  // the actor's input row and hidden layer live in the phase-2 partials:
+  // both are used between the step's last barrier and phase 2, and peers
+  // write the hidden layer only after that barrier
+  const size_t ain_n = (size_t)d.Bc * d.SRp, hx_n = d.Hx > 0 ? (size_t)d.Bc * d.Hxp : 0;
+  size_t p2 = (size_t)KS_MAX * d.Bc * d.U3p;
+  if (ain_n + hx_n > p2) p2 = ain_n + hx_n;
+  L.part2 = take(p2);
+  L.ain = L.part2;
+  L.hx = L.part2 + ain_n;
+  // actions are preloaded only when given (with an actor they are computed),
+  // and only while the preload fits beside everything else
+  const size_t na = d.Hx > 0 ? 0 : (size_t)T * d.Bc * d.A, ne = (size_t)T * d.Bc * d.S;
+  L.preload = (na + ne) * 4 <= PRELOAD_MAX &&
+              (o + ((na + 3) & ~size_t(3)) + ((ne + 3) & ~size_t(3))) * 4 <= SMEM_CAP;
+  L.act = take(L.preload ? na : 0);
+  L.eps = take(L.preload ? ne : 0);
   L.total = o;
   return L;
 }
@@ -229,13 +262,16 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
   const int q = blockIdx.x / RC;
   const int b0 = q * Bc;
   const int nr = min(Bc, p.B - b0);  // rows of this cluster (uniform across the cluster)
-  const Dims d = make_dims(p.S, p.A, p.Hd, p.RH, Bc);
+  const bool actor = p.Wa1 != nullptr;  // unroll variant 2: actions from the actor
+  const Dims d = make_dims(p.S, p.A, p.Hd, p.RH, Bc, actor ? p.Hx : 0);
   const Layout L = make_layout(d, p.T);
   const int S = d.S, A = d.A, Hd = d.Hd, RH = d.RH, SA = S + A;
   const int Hdp = d.Hdp, RHp = d.RHp, SAp = d.SAp;
   const int i0 = c * d.Ha, ni = max(0, min(d.Ha, Hd - i0));   // owned a / q outputs
   const int j0 = c * d.Ua, nj = max(0, min(d.Ua, RH - j0));   // owned GRU units
   const int s0 = c * d.Sa, ns = max(0, min(d.Sa, S - s0));    // owned state entries
+  const int x0 = c * d.Hxa, nx = actor ? max(0, min(d.Hxa, d.Hx - x0)) : 0;  // actor hidden
+  const int a0 = c * d.Axa, na = actor ? max(0, min(d.Axa, A - a0)) : 0;      // actions
   const int tid = threadIdx.x;
   const bool tr = p.trace && blockIdx.x == 0 && tid == 0;
   if (tr) p.trace[11] = globaltimer_ns();
@@ -264,6 +300,12 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
     const int h = o / d.Sa, j = o % d.Sa;
     sm[L.b3 + o] = (j < ns && p.b3) ? p.b3[h * S + s0 + j] : 0.f;
   }
+  if (actor) {
+    load_T(p.Wa1, S + RH, x0, nx, d.Hxa, d.Hxap, sm + L.wa1);
+    load_T(p.Wa2, d.Hx, a0, na, d.Axa, d.Axap, sm + L.wa2);
+    for (int o = tid; o < d.Hxa; o += NT) sm[L.ba1 + o] = (o < nx && p.ba1) ? p.ba1[x0 + o] : 0.f;
+    for (int o = tid; o < d.Axa; o += NT) sm[L.ba2 + o] = (o < na && p.ba2) ? p.ba2[a0 + o] : 0.f;
+  }
   // ---- initial state / belief of the cluster's rows (full vectors, every CTA)
   for (int e = tid; e < Bc * S; e += NT) {
     const int r = e / S, k = e % S;
@@ -275,7 +317,7 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
         (r < nr && p.belief0) ? p.belief0[(size_t)(b0 + r) * RH + k] : 0.f;
   }
   if (L.preload) {
-    for (int e = tid; e < p.T * Bc * A; e += NT) {
+    for (int e = tid; e < (actor ? 0 : p.T * Bc * A); e += NT) {
       const int t = e / (Bc * A), r = (e / A) % Bc, k = e % A;
       sm[L.act + e] = r < nr ? p.actions[((size_t)t * p.B + b0 + r) * A + k] : 0.f;
     }
@@ -295,6 +337,7 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
   const int ks2a = split_of(d.U3p, Hd), ks2b = split_of(d.U3p, RH);
   const int ks3 = split_of(d.Hap, RH);
   const int ks4 = split_of(d.S2p, Hd);
+  const int ksx1 = actor ? split_of(d.Hxap, S + RH) : 1, ksx2 = actor ? split_of(d.Axap, d.Hx) : 1;
   float *part1 = sm + L.part1, *part2 = sm + L.part2;
   float out_v[3] = {0.f, 0.f, 0.f};
   float *out_p[3] = {nullptr, nullptr, nullptr};
@@ -304,9 +347,47 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
     if (tr) p.trace[t * 16 + 0] = globaltimer_ns();
     float *bel_cur = sm + L.bel + (size_t)cur * Bc * RHp;
     const size_t bel_nxt = L.bel + (size_t)(cur ^ 1) * Bc * RHp;
-    // ---- phase 1: a = ELU(W1 [state, action] + b1), owned outputs
-    for (int e = tid; e < Bc * SA; e += NT) {
-      const int r = e / SA, k = e % SA;
+    if (actor) {
+      // ---- actor, hidden layer: x = ELU(Wa1 [state, belief] + ba1), owned outputs
+      const int SR = S + RH;
+      for (int e = tid; e < Bc * SR; e += NT) {
+        const int r = e / SR, k = e % SR;
+        sm[L.ain + (size_t)r * d.SRp + k] =
+            k < S ? sm[L.st + (size_t)r * S + k] : bel_cur[(size_t)r * RHp + (k - S)];
+      }
+      __syncthreads();
+      matvec_part<NR>(sm + L.wa1, d.Hxap, SR, sm + L.ain, d.SRp, ksx1, part1);
+      __syncthreads();
+      reduce_parts(part1, d.Hxap, Bc, ksx1);
+      __syncthreads();
+      for (int e = tid; e < nx * Bc; e += NT) {
+        const int o = e % nx, r = e / nx;
+        const float xv = elu_f(part_sum(part1, d.Hxap, r, o) + sm[L.ba1 + o]);
+#pragma unroll
+        for (int q2 = 0; q2 < RC; ++q2) rem[q2][L.hx + (size_t)r * d.Hxp + x0 + o] = xv;
+      }
+      cluster.sync();
+      // ---- actor, output: action = tanh(Wa2 x + ba2), owned entries, placed
+      //      straight into every CTA's phase-1 input row
+      matvec_part<NR>(sm + L.wa2, d.Axap, d.Hx, sm + L.hx, d.Hxp, ksx2, part1);
+      __syncthreads();
+      reduce_parts(part1, d.Axap, Bc, ksx2);
+      __syncthreads();
+      for (int e = tid; e < na * Bc; e += NT) {
+        const int j = e % na, r = e / na;
+        const float av = tanh_f(part_sum(part1, d.Axap, r, j) + sm[L.ba2 + j]);
+#pragma unroll
+        for (int q2 = 0; q2 < RC; ++q2) rem[q2][L.in1 + (size_t)r * SAp + S + a0 + j] = av;
+        if (r < nr && p.actions_out) p.actions_out[((size_t)t * p.B + b0 + r) * A + a0 + j] = av;
+      }
+      cluster.sync();
+      if (tr) p.trace[t * 16 + 5] = globaltimer_ns();
+    }
+    // ---- phase 1: a = ELU(W1 [state, action] + b1), owned outputs (with the
+    //      actor only the state part of the input row is filled here)
+    for (int e = tid; e < Bc * (actor ? S : SA); e += NT) {
+      const int SW = actor ? S : SA;
+      const int r = e / SW, k = e % SW;
       float v;
       if (k < S) v = sm[L.st + (size_t)r * S + k];
       else if (L.preload) v = sm[L.act + ((size_t)t * Bc + r) * A + (k - S)];
@@ -432,15 +513,15 @@ cudaError_t launch_nr(const RssmParams &p, int Bc, int grid, size_t smem, cudaSt
   return cudaGetLastError();
 }
 
-size_t smem_bytes(int S, int A, int Hd, int RH, int Bc, int T) {
-  return make_layout(make_dims(S, A, Hd, RH, Bc), T).total * sizeof(float);
+size_t smem_bytes(int S, int A, int Hd, int RH, int Bc, int T, int Hx = 0) {
+  return make_layout(make_dims(S, A, Hd, RH, Bc, Hx), T).total * sizeof(float);
 }
 
 }  // namespace
 
-bool rssm_supported(int S, int A, int Hd, int RH) {
-  if (S < 1 || A < 0 || Hd < 1 || RH < 1) return false;
-  return smem_bytes(S, A, Hd, RH, 1, 0) <= 227 * 1024;
+bool rssm_supported(int S, int A, int Hd, int RH, int Hx) {
+  if (S < 1 || A < 0 || Hd < 1 || RH < 1 || Hx < 0 || (Hx > 0 && A < 1)) return false;
+  return smem_bytes(S, A, Hd, RH, 1, 0, Hx) <= SMEM_CAP;
 }
 
 // Clusters of RC CTAs that can be resident at once with this shared-memory
@@ -482,17 +563,18 @@ int resident_clusters(size_t smem, int Bc, int nsm) {
 }
 
 cudaError_t launch_rssm(const RssmParams &p, int nsm, cudaStream_t s, int *clusters_used) {
+  const int hx = p.Wa1 ? p.Hx : 0;
   int Bc = pick_bc(p.B, nsm);
-  while (Bc > 1 && smem_bytes(p.S, p.A, p.Hd, p.RH, Bc, p.T) > 227 * 1024) --Bc;
+  while (Bc > 1 && smem_bytes(p.S, p.A, p.Hd, p.RH, Bc, p.T, hx) > SMEM_CAP) --Bc;
   // all clusters should be resident together: grow the batch slice until they are
   for (int it = 0; it < MAXBC; ++it) {
-    const int room = resident_clusters(smem_bytes(p.S, p.A, p.Hd, p.RH, Bc, p.T), Bc, nsm);
+    const int room = resident_clusters(smem_bytes(p.S, p.A, p.Hd, p.RH, Bc, p.T, hx), Bc, nsm);
     if (ceil_div(p.B, Bc) <= room || Bc >= MAXBC) break;
-    if (smem_bytes(p.S, p.A, p.Hd, p.RH, Bc + 1, p.T) > 227 * 1024) break;
+    if (smem_bytes(p.S, p.A, p.Hd, p.RH, Bc + 1, p.T, hx) > SMEM_CAP) break;
     ++Bc;
   }
-  const size_t smem = smem_bytes(p.S, p.A, p.Hd, p.RH, Bc, p.T);
-  if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
+  const size_t smem = smem_bytes(p.S, p.A, p.Hd, p.RH, Bc, p.T, hx);
+  if (smem > SMEM_CAP) return cudaErrorInvalidConfiguration;
   const int clusters = ceil_div(p.B, Bc);
   if (clusters_used) *clusters_used = clusters;
   switch (Bc) {

@@ -20,7 +20,7 @@ from . import binding
 from . import workloads as wl
 
 WORKLOADS = {"lstm": wl.LSTM_T80, "rssm": wl.RSSM_B50, "lstmp": wl.LSTMP_2L,
-             "bilstm": wl.BILSTM_VAR, "gru": wl.GRU_3L}
+             "bilstm": wl.BILSTM_VAR, "gru": wl.GRU_3L, "rssm_actor": wl.RSSM_ACTOR}
 
 # (from slot, to slot, label) per kernel
 PHASES = {
@@ -34,7 +34,8 @@ PHASES = {
     "recurrent_simt": [(0, 3, "h_{t-1} rows loaded"), (3, 4, "mat-vec"),
                        (4, 1, "gates, h_t stored"), (1, 2, "step barrier")],
     "recurrent_cluster": [(0, 3, "mat-vec"), (3, 4, "gates"), (4, 1, "h_t sent")],
-    "rssm": [(0, 1, "Linear+ELU on [state, action]"), (1, 2, "GRUCell"),
+    "rssm": [(0, 5, "actor: ELU layer, tanh layer"), (5, 1, "Linear+ELU on [state, action]"),
+             (0, 1, "[actor and] Linear+ELU on [state, action]"), (1, 2, "GRUCell"),
              (2, 3, "Linear+ELU"), (3, 4, "Linear, softplus, sample")],
 }
 
@@ -60,11 +61,17 @@ def run(workload: str, T: int = 0, ksplit: int = 0, seed: int = 0):
         inp = wl.make_rssm_inputs(spec, seed=seed)
         m = binding.RSSM(spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden)
         m.set_weights(inp["weights"])
-        a, e = inp["actions"].to(dev), inp["eps"].to(dev)
+        e = inp["eps"].to(dev)
+        if spec.actor_hidden:
+            m.set_actor(inp["actor"])
+            run1 = lambda: m.unroll_actor(e)  # noqa: E731
+        else:
+            a = inp["actions"].to(dev)
+            run1 = lambda: m.unroll(a, e)  # noqa: E731
         for _ in range(3):
-            m.unroll(a, e)
+            run1()
         binding.rssm_set_attr(m.h, binding.RCU_ATTR_TRACE, 1)
-        m.unroll(a, e)
+        run1()
         tr = binding.rssm_get_trace(m.h, spec.T).numpy().astype(np.float64)
         kernel = "rssm"
     else:

@@ -10,9 +10,10 @@ x; then lengths; then h0, c0; then (RSSM) actions and eps.  Weights and biases
 follow the PyTorch module default, U(-1/sqrt(hidden), 1/sqrt(hidden)); RSSM
 Linear layers use U(-1/sqrt(fan_in), 1/sqrt(fan_in)).
 
-The five named workloads are the shapes the pages discuss: the TVM TE LSTM
+The named workloads are the shapes the pages discuss: the TVM TE LSTM
 benchmark shape (T=80, B=1, 512 -> 256), the dreamer/planet RSSM prior
-(state 20, hidden 200), a speech-style projected LSTM at T=1000, a
+(state 20, hidden 200; with given actions, and with an actor of width 200
+computing them on the fly), a speech-style projected LSTM at T=1000, a
 variable-length bidirectional LSTM, and a large stacked GRU.
 """
 from __future__ import annotations
@@ -67,6 +68,8 @@ class RssmSpec:
     rnn_hidden: int = 200
     state0_std: float = 0.0
     belief0_std: float = 0.0
+    # unroll variant 2: actions from an actor of this hidden width (0 = given)
+    actor_hidden: int = 0
 
     def scaled(self, **kw) -> "RssmSpec":
         return dataclasses.replace(self, **kw)
@@ -74,6 +77,7 @@ class RssmSpec:
 
 LSTM_T80 = RnnSpec("lstm_f32_T80_B1_512x256", "lstm", 1, 512, 256, T=80, B=1)
 RSSM_B50 = RssmSpec("rssm_f32_B50_T50_S20_A6_H200", T=50, B=50)
+RSSM_ACTOR = RssmSpec("rssm_actor_f32_B50_T50_S20_A6_H200_X200", T=50, B=50, actor_hidden=200)
 LSTMP_2L = RnnSpec("lstmp_bf16_2L_T1000_B32_80x1024p256", "lstm", 2, 80, 1024, T=1000, B=32,
                    proj=256, dtype="bf16")
 BILSTM_VAR = RnnSpec("bilstm_f32_varlen_B64_T500_256x512", "lstm", 1, 256, 512, T=500, B=64,
@@ -81,7 +85,8 @@ BILSTM_VAR = RnnSpec("bilstm_f32_varlen_B64_T500_256x512", "lstm", 1, 256, 512, 
 GRU_3L = RnnSpec("gru_bf16_3L_T512_B256_1024", "gru", 3, 1024, 1024, T=512, B=256, dtype="bf16",
                  h0_std=0.1)
 
-WORKLOADS = {s.name: s for s in (LSTM_T80, RSSM_B50, LSTMP_2L, BILSTM_VAR, GRU_3L)}
+WORKLOADS = {s.name: s for s in (LSTM_T80, RSSM_B50, LSTMP_2L, BILSTM_VAR, GRU_3L,
+                                  RSSM_ACTOR)}
 
 
 def _uniform(g, shape, bound):
@@ -120,7 +125,9 @@ def make_rnn_inputs(spec: RnnSpec, seed: int = 0, bias: bool = True) -> dict:
 
 
 def make_rssm_inputs(spec: RssmSpec, seed: int = 0) -> dict:
-    """RSSM prior weights, actions ~ U(-1, 1), eps ~ N(0, 1), zero or random start."""
+    """RSSM prior weights, actions ~ U(-1, 1), eps ~ N(0, 1), zero or random start.
+    With spec.actor_hidden the actions are replaced by the actor's weights
+    ("actor", make_rssm_actor); every other draw stays the same."""
     g = torch.Generator().manual_seed(seed)
     S, A, Hd, RH = spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden
     b1 = 1.0 / math.sqrt(S + A)
@@ -141,7 +148,11 @@ def make_rssm_inputs(spec: RssmSpec, seed: int = 0) -> dict:
         state0 = torch.randn((spec.B, S), generator=g, dtype=torch.float32) * spec.state0_std
     if spec.belief0_std > 0:
         belief0 = torch.randn((spec.B, RH), generator=g, dtype=torch.float32) * spec.belief0_std
-    return {"weights": w, "actions": actions, "eps": eps, "state0": state0, "belief0": belief0}
+    out = {"weights": w, "actions": actions, "eps": eps, "state0": state0, "belief0": belief0}
+    if spec.actor_hidden:
+        out["actions"] = None
+        out["actor"] = make_rssm_actor(spec, seed, spec.actor_hidden)
+    return out
 
 
 def make_rssm_actor(spec: RssmSpec, seed: int = 0, actor_hidden: int = 0) -> dict:

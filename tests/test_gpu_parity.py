@@ -477,6 +477,58 @@ def test_rssm_parity(spec):
     m.close()
 
 
+@pytest.mark.parametrize("spec,hx", [
+    (wl.RSSM_B50, 0),   # actor hidden width = the prior's hidden width
+    (wl.RSSM_B50.scaled(T=9, B=70, state_dim=13, action_dim=5, hidden=72, rnn_hidden=40,
+                        state0_std=1.0, belief0_std=0.5), 37),
+    (wl.RSSM_B50.scaled(T=3, B=1, state_dim=4, action_dim=11, hidden=16, rnn_hidden=9), 3),
+], ids=lambda v: getattr(v, "name", f"hx{v}"))
+def test_rssm_actor_parity(spec, hx):
+    """Unroll variant 2: the actions come from the actor on the device and
+    are fed back; every output and the actions match the oracle."""
+    inp = wl.make_rssm_inputs(spec, seed=23)
+    actor = wl.make_rssm_actor(spec, seed=23, actor_hidden=hx)
+    dev = torch.device("cuda")
+    m = binding.RSSM(spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden)
+    m.set_weights(inp["weights"])
+    m.set_actor(actor)
+    s0 = inp["state0"].to(dev) if inp["state0"] is not None else None
+    b0 = inp["belief0"].to(dev) if inp["belief0"] is not None else None
+    outs = m.unroll_actor(inp["eps"].to(dev), s0, b0)
+    assert binding.rssm_get_status(m.h) == 0
+    assert m.launch_count() == 1
+    ref = oracle.rssm_unroll_actor(inp["weights"], actor, inp["eps"], state0=inp["state0"],
+                                   belief0=inp["belief0"])
+    for name, o, r in zip(("means", "stds", "states", "beliefs", "actions"), outs, ref):
+        e = float(np.abs(o.cpu().numpy() - r).max())
+        assert e <= F32_TOL, f"{name}: max-abs error {e:.3e}"
+    # the given-actions unroll of the same handle is unaffected by the actor
+    got = m.unroll(outs[4], inp["eps"].to(dev), s0, b0)
+    for o, r in zip(got, outs[:4]):
+        assert float((o - r).abs().max()) <= F32_TOL
+    m.close()
+
+
+def test_rssm_actor_errors():
+    spec = wl.RSSM_B50.scaled(T=2, B=2, state_dim=4, action_dim=3, hidden=8, rnn_hidden=8)
+    inp = wl.make_rssm_inputs(spec, seed=1)
+    dev = torch.device("cuda")
+    m = binding.RSSM(spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden)
+    m.set_weights(inp["weights"])
+    with pytest.raises(RuntimeError, match="actor not set"):
+        m.unroll_actor(inp["eps"].to(dev))
+    # an actor wider than one cluster's shared memory holds
+    big = wl.make_rssm_actor(spec, actor_hidden=40000)
+    with pytest.raises(RuntimeError, match="shared memory"):
+        m.set_actor(big)
+    m.close()
+    m0 = binding.RSSM(spec.state_dim, 0, spec.hidden, spec.rnn_hidden)
+    m0.set_weights(wl.make_rssm_inputs(spec.scaled(action_dim=0), seed=1)["weights"])
+    with pytest.raises(RuntimeError, match="action_dim"):
+        m0.set_actor(wl.make_rssm_actor(spec.scaled(action_dim=1), actor_hidden=4))
+    m0.close()
+
+
 # ----------------------------------------------------------------------------- full-size workloads
 
 FULL = [
