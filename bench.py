@@ -225,8 +225,19 @@ def make_runner(spec, inp, dev, tc_ksplit=0):
             return None
 
         def e2e_io():
-            ins = {k: v for k, v in d.items() if v is not None}
-            return ins, outs
+            # pinned host buffers through the host-buffer entry point
+            hin = {k: (None if inp[k] is None else inp[k].contiguous().pin_memory())
+                   for k in ("state0", "belief0", "actions", "eps")}
+            hout = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+
+            def call():
+                if spec.actor_hidden:
+                    binding.rssm_unroll_actor_host(m.h, T, B, hin["state0"], hin["belief0"],
+                                                   hin["eps"], *hout)
+                else:
+                    binding.rssm_unroll_host(m.h, T, B, hin["state0"], hin["belief0"],
+                                             hin["actions"], hin["eps"], *hout)
+            return [v for v in hin.values() if v is not None], hout, call
 
         def status():
             return binding.rssm_get_status(m.h)
@@ -259,9 +270,16 @@ def make_runner(spec, inp, dev, tc_ksplit=0):
         return prof
 
     def e2e_io():
-        ins = {k: v for k, v in d.items() if v is not None}
-        outs = [y, hn] + ([cn] if cn is not None else [])
-        return ins, outs
+        # pinned host buffers through the host-buffer entry point
+        hin = {k: (None if inp[k] is None else inp[k].contiguous().pin_memory())
+               for k in ("x", "lengths", "h0", "c0")}
+        hout = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in (y, hn)] + \
+            ([torch.empty(cn.shape, dtype=cn.dtype, pin_memory=True)] if cn is not None else [None])
+
+        def call():
+            binding.rnn_forward_host(net.h, T, B, hin["x"], hin["lengths"], hin["h0"], hin["c0"],
+                                     *hout)
+        return [v for v in hin.values() if v is not None], [o for o in hout if o is not None], call
 
     def status():
         return net.status()
@@ -356,12 +374,11 @@ def run_ours(args, spec, rank, local, ws):
     all_units = dist_sum(units(spec, inp) * args.steps, dev)
     value = all_units / (max_ms / 1e3)
 
-    # ---- end to end: pinned host inputs -> device, forward, result -> host
-    ins, outs = e2e_io()
-    host_in = {k: v.cpu().pin_memory() for k, v in ins.items()}
-    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = sum(o.numel() * o.element_size() for o in outs)
+    # ---- end to end: the library's host-buffer entry point on pinned host
+    #      inputs and outputs (every byte crosses the CPU-GPU link each step)
+    host_in, host_out, host_call = e2e_io()
+    h2d = sum(v.numel() * v.element_size() for v in host_in)
+    d2h = sum(o.numel() * o.element_size() for o in host_out)
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
     for it in range(e2e_steps + 1):
         if it == 1:
@@ -369,11 +386,7 @@ def run_ours(args, spec, rank, local, ws):
             torch.cuda.synchronize(dev)
             ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             ea.record(stream)
-        for k, v in host_in.items():
-            ins[k].copy_(v, non_blocking=True)
-        step()
-        for o, h in zip(outs, host_out):
-            h.copy_(o, non_blocking=True)
+        host_call()
     eb.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = dist_max(ea.elapsed_time(eb) / e2e_steps, dev)
@@ -401,7 +414,10 @@ def run_ours(args, spec, rank, local, ws):
         "kernels": {k: {"ms_total": round(v[0], 3), "launches": v[1]} for k, v in prof.items()}
         if prof else None,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+                "call": ("rssm_unroll_actor_host" if getattr(spec, "actor_hidden", 0) else
+                         "rssm_unroll_host") if isinstance(spec, wl.RssmSpec) else
+                "rnn_forward_host", "host_buffers": "pinned"},
         "gpu_launches": n_launch,
         "clocks": clk,
         "wall_s_timed_region": round(wall, 3),

@@ -89,6 +89,12 @@ typedef struct rcu_rssm_s *rcu_rssm_t;
 #define RCU_ATTR_PROFILE 4            /* 1 = record a CUDA event pair around every kernel
                                          this handle launches (on the launching stream);
                                          read the totals with rnn_profile_entry */
+#define RCU_ATTR_HOST_CHUNKS 8        /* rnn_forward_host: chunks of steps whose host<->device
+                                         copies overlap the other chunks' compute (0 =
+                                         automatic, 1 = none, up to RCU_MAX_HOST_CHUNKS;
+                                         unidirectional networks without projection or
+                                         lengths, x and y page-locked) */
+#define RCU_MAX_HOST_CHUNKS 16
 
 /* Clipping targets for rnn_set_clip. */
 #define RCU_CLIP_CELL 0 /* LSTM cell state c_t */
@@ -156,6 +162,34 @@ RCU_API int rnn_set_weights(rcu_rnn_t h, int layer, int dir, const float *W_ih, 
 RCU_API int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int32_t *lengths,
                 const float *h0, const float *c0, const float *eps, float *y, float *h_n,
                 float *c_n, void *stream);
+
+/*
+ * rnn_forward with every buffer in host memory (the same arguments, eps
+ * dropped; lengths is a host int32 array).  Nothing is allocated per call
+ * beyond staging buffers the handle keeps.
+ *   - x and y: when page-locked and registered with CUDA (cudaHostAlloc,
+ *     cudaHostRegister, torch pin_memory), the kernels read x and write y in
+ *     place through their device addresses over the coherent CPU-GPU link
+ *     (NVLink-C2C on Grace-Blackwell): the host<->device transfer happens
+ *     inside the packing kernel (x) and the last layer's kernels (y, off the
+ *     recurrence's critical path).  Pageable x / y are staged through device
+ *     buffers with cudaMemcpyAsync.
+ *   - lengths, h0, c0 are copied in, h_n, c_n copied out (small).
+ *   - Chunked pipeline (RCU_ATTR_HOST_CHUNKS; automatic from 64 MB of x + y,
+ *     one chunk per 64 steps, at most 8): for a unidirectional network
+ *     without projection or lengths, with page-locked x and y, the steps
+ *     are run in chunks,
+ *     each a forward of all layers from every layer's state after the
+ *     previous chunk (kept in fp32, so the results equal the unchunked
+ *     ones).  x and y then move by cudaMemcpyAsync on two streams the handle
+ *     owns, overlapping the other chunks' compute.  rnn_get_pack then
+ *     describes the last chunk.
+ * Results are in host memory once `stream` has passed this call.  Errors
+ * as rnn_forward.
+ */
+RCU_API int rnn_forward_host(rcu_rnn_t h, int T, int B, const float *x, const int32_t *lengths,
+                             const float *h0, const float *c0, float *y, float *h_n, float *c_n,
+                             void *stream);
 
 /*
  * Copy the packing metadata of the last rnn_forward (device int32 buffers):
@@ -304,6 +338,22 @@ RCU_API int rssm_unroll_actor(rcu_rssm_t h, int T, int B, const float *state0,
                               const float *belief0, const float *eps, float *means,
                               float *stds, float *states, float *beliefs, float *actions_out,
                               void *stream);
+
+/*
+ * Host-buffer forms of rssm_unroll and rssm_unroll_actor (same arguments, all
+ * in host memory).  state0, belief0, actions and eps are copied in; each
+ * output that is page-locked and registered with CUDA is written in place by
+ * the kernel over the CPU-GPU link, a pageable one is staged and copied back.
+ * Results are in host memory once `stream` has passed the call.
+ */
+RCU_API int rssm_unroll_host(rcu_rssm_t h, int T, int B, const float *state0,
+                             const float *belief0, const float *actions, const float *eps,
+                             float *means, float *stds, float *states, float *beliefs,
+                             void *stream);
+RCU_API int rssm_unroll_actor_host(rcu_rssm_t h, int T, int B, const float *state0,
+                                   const float *belief0, const float *eps, float *means,
+                                   float *stds, float *states, float *beliefs, float *actions_out,
+                                   void *stream);
 
 /*
  * Unroll T steps for B independent rows with given actions.  Per step:

@@ -29,6 +29,7 @@ RCU_ERR_TIMEOUT, RCU_ERR_LENGTHS, RCU_ERR_STATE = -4, -5, -6
 RCU_ATTR_BARRIER_TIMEOUT_NS, RCU_ATTR_TEST_DROP_ARRIVAL, RCU_ATTR_FORCE_PATH = 1, 2, 3
 RCU_ATTR_PROFILE, RCU_ATTR_TRACE, RCU_ATTR_TC_CLUSTER, RCU_ATTR_TC_KSPLIT = 4, 5, 6, 7
 RCU_CLIP_CELL, RCU_CLIP_PROJ = 0, 1
+RCU_ATTR_HOST_CHUNKS, RCU_MAX_HOST_CHUNKS = 8, 16
 
 EXPORTED = (
     "rcu_last_error", "rcu_version", "rnn_create", "rnn_set_weights", "rnn_forward",
@@ -37,7 +38,8 @@ EXPORTED = (
     "rnn_profile_entry", "rnn_profile_reset", "rnn_get_trace", "rnn_lstm_forward_noalloc",
     "rssm_create", "rssm_set_weights", "rssm_unroll", "rssm_get_status",
     "rssm_last_launch_count", "rssm_destroy", "rssm_set_attr", "rssm_get_trace",
-    "rssm_set_actor", "rssm_unroll_actor",
+    "rssm_set_actor", "rssm_unroll_actor", "rnn_forward_host", "rssm_unroll_host",
+    "rssm_unroll_actor_host",
 )
 
 _lib = None
@@ -93,6 +95,9 @@ def load(path: Optional[str] = None):
             "rssm_get_trace": (I, [P, P, I, P]),
             "rssm_set_actor": (I, [P, I, P, P, P, P, P]),
             "rssm_unroll_actor": (I, [P, I, I] + [P] * 8 + [P]),
+            "rnn_forward_host": (I, [P, I, I] + [P] * 8),
+            "rssm_unroll_host": (I, [P, I, I] + [P] * 8 + [P]),
+            "rssm_unroll_actor_host": (I, [P, I, I] + [P] * 8 + [P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -129,6 +134,23 @@ def _dev(t: Optional[torch.Tensor], dtype=torch.float32):
     if t.dtype != dtype:
         raise ValueError(f"expected {dtype}, got {t.dtype}")
     t = canonical_contiguous(t)
+    return t, ctypes.c_void_p(t.data_ptr())
+
+
+def _host(t: Optional[torch.Tensor], dtype=torch.float32, out=False):
+    """Host tensor -> (kept tensor, pointer).  Pinned tensors (pin_memory) are
+    used in place by the kernels; pageable ones are staged by the library."""
+    if t is None:
+        return None, None
+    if t.is_cuda:
+        raise ValueError("the *_host entry points take host tensors")
+    if t.dtype != dtype:
+        raise ValueError(f"expected {dtype}, got {t.dtype}")
+    if out:
+        if canonical_contiguous(t) is not t:
+            raise ValueError("outputs must be C-contiguous")
+    else:
+        t = canonical_contiguous(t)
     return t, ctypes.c_void_p(t.data_ptr())
 
 
@@ -227,6 +249,15 @@ def rnn_lstm_forward_noalloc(T: int, B: int, in_dim: int, hidden: int, x, W_ih, 
                                            *[k[1] for k in outs], _stream(stream)))
 
 
+def rnn_forward_host(h, T: int, B: int, x, lengths, h0, c0, y, h_n, c_n, stream=None):
+    """rnn_forward on host tensors (see rcu.h); results are in y/h_n/c_n once
+    the stream has passed the call."""
+    ins = [_host(x), _host(lengths, torch.int32), _host(h0), _host(c0)]
+    outs = [_host(t, out=True) for t in (y, h_n, c_n)]
+    _check(load().rnn_forward_host(h, T, B, *[k[1] for k in ins], *[k[1] for k in outs],
+                                   _stream(stream)))
+
+
 def rssm_create(state_dim: int, action_dim: int, hidden: int, rnn_hidden: int):
     h = ctypes.c_void_p()
     _check(load().rssm_create(ctypes.byref(h), state_dim, action_dim, hidden, rnn_hidden))
@@ -257,6 +288,22 @@ def rssm_unroll_actor(h, T: int, B: int, state0, belief0, eps, means, stds, stat
     outs = [_dev(t) for t in (means, stds, states, beliefs, actions_out)]
     _check(load().rssm_unroll_actor(h, T, B, *[k[1] for k in ins], *[k[1] for k in outs],
                                     _stream(stream)))
+
+
+def rssm_unroll_host(h, T: int, B: int, state0, belief0, actions, eps, means, stds, states,
+                     beliefs, stream=None):
+    ins = [_host(t) for t in (state0, belief0, actions, eps)]
+    outs = [_host(t, out=True) for t in (means, stds, states, beliefs)]
+    _check(load().rssm_unroll_host(h, T, B, *[k[1] for k in ins], *[k[1] for k in outs],
+                                   _stream(stream)))
+
+
+def rssm_unroll_actor_host(h, T: int, B: int, state0, belief0, eps, means, stds, states, beliefs,
+                           actions_out, stream=None):
+    ins = [_host(t) for t in (state0, belief0, eps)]
+    outs = [_host(t, out=True) for t in (means, stds, states, beliefs, actions_out)]
+    _check(load().rssm_unroll_actor_host(h, T, B, *[k[1] for k in ins],
+                                         *[k[1] for k in outs], _stream(stream)))
 
 
 def rssm_get_status(h, stream=None) -> int:

@@ -89,6 +89,74 @@ struct DevBuf {
   }
 };
 
+// ---- host buffers of the *_host entry points
+//
+// A host buffer that is page-locked and registered with CUDA (cudaHostAlloc,
+// cudaHostRegister, torch's pin_memory) has a device address: the kernels
+// read or write it in place over the coherent CPU-GPU link, so its copy
+// happens inside the kernel that touches it.  A pageable buffer is staged
+// through a device buffer with cudaMemcpyAsync.  Device (or managed) memory
+// passed here is used as it is.
+const void *device_address(const void *p) {
+  if (!p) return nullptr;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return p;
+  if (a.type == cudaMemoryTypeHost && a.devicePointer) return a.devicePointer;
+  return nullptr;  // pageable
+}
+
+struct HostIO {
+  cudaStream_t s;
+  struct Back { void *host; const void *dev; size_t bytes; };
+  std::vector<Back> back;
+  // input: in place when `in_place` and mapped, else copied to `stage`
+  cudaError_t in(const void *host, size_t bytes, DevBuf &stage, bool in_place, const void **out,
+                 bool *placed = nullptr) {
+    *out = nullptr;
+    if (placed) *placed = false;
+    if (!host || bytes == 0) return cudaSuccess;
+    if (in_place) {
+      if (const void *d = device_address(host)) {
+        *out = d;
+        if (placed) *placed = true;
+        return cudaSuccess;
+      }
+    }
+    cudaError_t e = stage.ensure(bytes);
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyAsync(stage.p, host, bytes, cudaMemcpyDefault, s);
+    *out = stage.p;
+    return e;
+  }
+  // output: in place when `in_place` and mapped, else staged and copied back by finish()
+  cudaError_t out(void *host, size_t bytes, DevBuf &stage, bool in_place, void **dst) {
+    *dst = nullptr;
+    if (!host || bytes == 0) return cudaSuccess;
+    if (in_place) {
+      if (const void *d = device_address(host)) {
+        *dst = const_cast<void *>(d);
+        return cudaSuccess;
+      }
+    }
+    cudaError_t e = stage.ensure(bytes);
+    if (e != cudaSuccess) return e;
+    back.push_back({host, stage.p, bytes});
+    *dst = stage.p;
+    return cudaSuccess;
+  }
+  cudaError_t finish() {
+    for (auto &b : back) {
+      cudaError_t e = cudaMemcpyAsync(b.host, b.dev, b.bytes, cudaMemcpyDefault, s);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
+};
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -134,6 +202,16 @@ struct rcu_rnn_s {
   float cclip_lo = 0.f, cclip_hi = 0.f, pclip_lo = 0.f, pclip_hi = 0.f;
   int launches = 0;
   bool used_tc_gemm = false, used_tc_rec = false;
+  // rnn_forward_host: staging buffers, and x read in place from host memory
+  // (then always through the packing kernel's plain loads)
+  DevBuf io_x, io_len, io_h0, io_c0, io_y, io_hn, io_cn;
+  bool x_in_place = false;
+  // rnn_forward_host over chunks of steps: two copy streams, double-buffered
+  // x / y chunks, ping-pong per-layer state, events
+  int host_chunks = 0;  // RCU_ATTR_HOST_CHUNKS
+  cudaStream_t cp_in = nullptr, cp_out = nullptr;
+  std::vector<cudaEvent_t> chunk_ev;
+  DevBuf io_xc[2], io_yc[2], io_st[2], io_ct[2];
   // opt-in per-step trace of the first layer's recurrent kernel
   bool trace = false;
   DevBuf trace_buf;
@@ -183,6 +261,9 @@ struct rcu_rnn_s {
   ~rcu_rnn_s() {
     for (auto &p : pending) { cudaEventDestroy(p.a); cudaEventDestroy(p.b); }
     for (auto e : pool) cudaEventDestroy(e);
+    for (auto e : chunk_ev) cudaEventDestroy(e);
+    if (cp_in) cudaStreamDestroy(cp_in);
+    if (cp_out) cudaStreamDestroy(cp_out);
   }
 };
 
@@ -308,6 +389,11 @@ extern "C" int rnn_set_attr(rcu_rnn_t h, int attr, int64_t value) {
     case RCU_ATTR_FORCE_PATH:
       if (value < 0 || value > 3) return fail(RCU_ERR_INVALID, "force_path must be 0, 1, 2 or 3");
       h->force_path = (int)value;
+      return RCU_OK;
+    case RCU_ATTR_HOST_CHUNKS:
+      if (value < 0 || value > RCU_MAX_HOST_CHUNKS)
+        return fail(RCU_ERR_INVALID, "host chunks must be 0 .. %d", RCU_MAX_HOST_CHUNKS);
+      h->host_chunks = (int)value;
       return RCU_OK;
     default: return fail(RCU_ERR_INVALID, "rnn_set_attr: unknown attribute %d", attr);
   }
@@ -546,7 +632,7 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
   int ldx = h->in_dim;
   const int32_t *M_dev = varlen ? h->meta.step_off + T : nullptr;
   const int Mmax = T * B;
-  if (varlen || bf) {
+  if (varlen || bf || h->x_in_place) {
     ldx = round_up(h->in_dim, 8);
     h->begin("pack_rows", s);
     if (bf)
@@ -731,6 +817,131 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
   return RCU_OK;
 }
 
+
+// rnn_forward_host over n chunks of steps.  A forward over steps [t0, t1)
+// needs only those steps' x and every layer's state at t0 (its h_n / c_n
+// after the previous chunk), so each chunk is one rnn_forward with the
+// per-layer state carried in fp32 device buffers: the results are the
+// unchunked ones.  Copy stream cp_in moves x chunk c+2 in while chunk c+1
+// computes, cp_out moves y chunk c out meanwhile; only the first chunk's x
+// and the last chunk's y are not hidden behind compute.
+static int forward_host_chunked(rcu_rnn_t h, int T, int B, int n, const float *x,
+                                const float *h0, const float *c0, float *y, float *h_n,
+                                float *c_n, cudaStream_t s) {
+  const int Tc = ceil_div(T, n);
+  n = ceil_div(T, Tc);
+  const size_t in_row = (size_t)B * h->in_dim, out_row = (size_t)B * h->D * h->Hout;
+  const size_t LDB = (size_t)h->layers * h->D * B;
+  const bool lstm = h->cell == RCU_LSTM;
+  if (!h->cp_in) CU(cudaStreamCreateWithFlags(&h->cp_in, cudaStreamNonBlocking));
+  if (!h->cp_out) CU(cudaStreamCreateWithFlags(&h->cp_out, cudaStreamNonBlocking));
+  while ((int)h->chunk_ev.size() < 3 * RCU_MAX_HOST_CHUNKS + 1) {
+    cudaEvent_t e;
+    CU(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    h->chunk_ev.push_back(e);
+  }
+  cudaEvent_t *ev_in = h->chunk_ev.data(), *ev_comp = ev_in + RCU_MAX_HOST_CHUNKS,
+              *ev_out = ev_comp + RCU_MAX_HOST_CHUNKS, ev_entry = ev_out[RCU_MAX_HOST_CHUNKS];
+  for (int i = 0; i < 2; ++i) {
+    CU(h->io_xc[i].ensure((size_t)Tc * in_row * 4));
+    CU(h->io_yc[i].ensure((size_t)Tc * out_row * 4));
+    CU(h->io_st[i].ensure(LDB * h->Hout * 4));
+    if (lstm) CU(h->io_ct[i].ensure(LDB * h->H * 4));
+  }
+  HostIO io{s, {}};
+  const void *dh0, *dc0;
+  CU(io.in(h0, LDB * h->Hout * 4, h->io_h0, false, &dh0));
+  CU(io.in(c0, LDB * h->H * 4, h->io_c0, false, &dc0));
+  // the copy streams start after the work already on s
+  CU(cudaEventRecord(ev_entry, s));
+  CU(cudaStreamWaitEvent(h->cp_in, ev_entry, 0));
+  CU(cudaStreamWaitEvent(h->cp_out, ev_entry, 0));
+  auto steps_of = [&](int c) { return std::min(Tc, T - c * Tc); };
+  auto copy_in = [&](int c) -> cudaError_t {
+    cudaError_t e = cudaMemcpyAsync(h->io_xc[c & 1].p, x + (size_t)c * Tc * in_row,
+                                    (size_t)steps_of(c) * in_row * 4, cudaMemcpyDefault,
+                                    h->cp_in);
+    return e != cudaSuccess ? e : cudaEventRecord(ev_in[c], h->cp_in);
+  };
+  for (int c = 0; c < std::min(n, 2); ++c) CU(copy_in(c));
+  int launches = 0;
+  for (int c = 0; c < n; ++c) {
+    const int k = c & 1;
+    CU(cudaStreamWaitEvent(s, ev_in[c], 0));
+    if (c >= 2) CU(cudaStreamWaitEvent(s, ev_out[c - 2], 0));  // y buffer k is free again
+    const float *sh = c == 0 ? (const float *)dh0 : (const float *)h->io_st[k ^ 1].p;
+    const float *sc = c == 0 ? (const float *)dc0 : (lstm ? (const float *)h->io_ct[k ^ 1].p : nullptr);
+    const int rc = rnn_forward(h, steps_of(c), B, (const float *)h->io_xc[k].p, nullptr, sh, sc,
+                               nullptr, (float *)h->io_yc[k].p, (float *)h->io_st[k].p,
+                               lstm ? (float *)h->io_ct[k].p : nullptr, s);
+    if (rc != RCU_OK) return rc;
+    launches += h->launches;
+    CU(cudaEventRecord(ev_comp[c], s));
+    CU(cudaStreamWaitEvent(h->cp_out, ev_comp[c], 0));
+    CU(cudaMemcpyAsync(y + (size_t)c * Tc * out_row, h->io_yc[k].p,
+                       (size_t)steps_of(c) * out_row * 4, cudaMemcpyDefault, h->cp_out));
+    CU(cudaEventRecord(ev_out[c], h->cp_out));
+    if (c + 2 < n) {  // x buffer k is free once chunk c has computed
+      CU(cudaStreamWaitEvent(h->cp_in, ev_comp[c], 0));
+      CU(copy_in(c + 2));
+    }
+  }
+  // the call is complete on s once the last y chunk has landed
+  CU(cudaStreamWaitEvent(s, ev_out[n - 1], 0));
+  const int kl = (n - 1) & 1;
+  if (h_n) CU(cudaMemcpyAsync(h_n, h->io_st[kl].p, LDB * h->Hout * 4, cudaMemcpyDefault, s));
+  if (c_n) CU(cudaMemcpyAsync(c_n, h->io_ct[kl].p, LDB * h->H * 4, cudaMemcpyDefault, s));
+  h->launches = launches;
+  return RCU_OK;
+}
+
+extern "C" int rnn_forward_host(rcu_rnn_t h, int T, int B, const float *x, const int32_t *lengths,
+                                const float *h0, const float *c0, float *y, float *h_n,
+                                float *c_n, void *stream) {
+  if (!h) return fail(RCU_ERR_INVALID, "rnn_forward_host: NULL handle");
+  h->launches = 0;
+  if (T < 0 || B < 0) return fail(RCU_ERR_INVALID, "rnn_forward_host: T and B must be >= 0");
+  if (T == 0 || B == 0) return rnn_forward(h, T, B, x, lengths, h0, c0, nullptr, y, h_n, c_n, stream);
+  if (!x || !y) return fail(RCU_ERR_INVALID, "rnn_forward_host: x and y are required");
+  if (h->cell == RCU_GRU && (c0 || c_n))
+    return fail(RCU_ERR_INVALID, "rnn_forward_host: c0/c_n are LSTM-only");
+  for (auto &w : h->lw)
+    if (!w.set) return fail(RCU_ERR_STATE, "rnn_forward_host: weights missing for some layer/direction");
+  const size_t TB = (size_t)T * B, LDB = (size_t)h->layers * h->D * B;
+  const size_t x_bytes = TB * h->in_dim * 4, y_bytes = TB * h->D * h->Hout * 4;
+  // chunked pipeline: unidirectional, no lengths, no projection (the folded
+  // LSTMP path takes an initial state through a separate fp32 term, which
+  // would round differently from the recurrence it replaces), x and y
+  // page-locked (so the copies are asynchronous); automatic for transfers of
+  // 64 MB and more, one chunk per 64 steps up to 8
+  int n = h->host_chunks;
+  if (n == 0) n = x_bytes + y_bytes >= ((size_t)64 << 20) ? std::min(8, T / 64) : 1;
+  n = std::min(n, T);
+  if (n > 1 && h->D == 1 && h->P == 0 && !lengths && device_address(x) && device_address(y))
+    return forward_host_chunked(h, T, B, n, x, h0, c0, y, h_n, c_n, (cudaStream_t)stream);
+
+  HostIO io{(cudaStream_t)stream, {}};
+  const void *dx, *dlen, *dh0, *dc0;
+  void *dy, *dhn, *dcn;
+  bool x_placed = false;
+  // x read and y written in place when page-locked; the small buffers staged
+  CU(io.in(x, x_bytes, h->io_x, true, &dx, &x_placed));
+  CU(io.in(lengths, (size_t)B * 4, h->io_len, false, &dlen));
+  CU(io.in(h0, LDB * h->Hout * 4, h->io_h0, false, &dh0));
+  CU(io.in(c0, LDB * h->H * 4, h->io_c0, false, &dc0));
+  CU(io.out(y, y_bytes, h->io_y, true, &dy));
+  CU(io.out(h_n, LDB * h->Hout * 4, h->io_hn, false, &dhn));
+  CU(io.out(c_n, LDB * h->H * 4, h->io_cn, false, &dcn));
+  h->x_in_place = x_placed;
+  const int rc = rnn_forward(h, T, B, (const float *)dx, (const int32_t *)dlen,
+                             (const float *)dh0, (const float *)dc0, nullptr, (float *)dy,
+                             (float *)dhn, (float *)dcn, stream);
+  h->x_in_place = false;
+  if (rc != RCU_OK) return rc;
+  CU(io.finish());
+  return RCU_OK;
+}
+
 extern "C" int rnn_get_pack(rcu_rnn_t h, int32_t *sorted_idx, int32_t *unsorted_idx,
                             int32_t *batch_sizes, void *stream) {
   if (!h) return fail(RCU_ERR_INVALID, "rnn_get_pack: NULL handle");
@@ -819,6 +1030,8 @@ struct rcu_rssm_s {
   bool trace = false;
   DevBuf trace_buf;
   int trace_T = 0;
+  // rssm_unroll_host / rssm_unroll_actor_host staging buffers
+  DevBuf io_s0, io_b0, io_act, io_eps, io_out[5];
 };
 
 extern "C" int rssm_set_attr(rcu_rssm_t h, int attr, int64_t value) {
@@ -960,6 +1173,51 @@ extern "C" int rssm_unroll_actor(rcu_rssm_t h, int T, int B, const float *state0
                                  float *states, float *beliefs, float *actions_out, void *stream) {
   return rssm_run(h, true, T, B, state0, belief0, nullptr, eps, means, stds, states, beliefs,
                   actions_out, stream);
+}
+
+// Host-buffer form of both unrolls: inputs staged, outputs in place when
+// page-locked (written by the kernel over the CPU-GPU link), else staged.
+static int rssm_run_host(rcu_rssm_t h, bool with_actor, int T, int B, const float *state0,
+                         const float *belief0, const float *actions, const float *eps,
+                         float *means, float *stds, float *states, float *beliefs,
+                         float *actions_out, void *stream) {
+  if (!h) return fail(RCU_ERR_INVALID, "rssm host unroll: NULL handle");
+  if (T <= 0 || B <= 0)
+    return rssm_run(h, with_actor, T, B, state0, belief0, actions, eps, means, stds, states,
+                    beliefs, actions_out, stream);
+  const size_t TB = (size_t)T * B;
+  HostIO io{(cudaStream_t)stream, {}};
+  const void *ds0, *db0, *dact, *deps;
+  CU(io.in(state0, (size_t)B * h->S * 4, h->io_s0, false, &ds0));
+  CU(io.in(belief0, (size_t)B * h->RH * 4, h->io_b0, false, &db0));
+  CU(io.in(with_actor ? nullptr : actions, TB * h->A * 4, h->io_act, false, &dact));
+  CU(io.in(eps, TB * h->S * 4, h->io_eps, false, &deps));
+  void *d[5];
+  float *outs[5] = {means, stds, states, beliefs, actions_out};
+  const size_t w[5] = {(size_t)h->S, (size_t)h->S, (size_t)h->S, (size_t)h->RH, (size_t)h->A};
+  for (int i = 0; i < 5; ++i) CU(io.out(outs[i], TB * w[i] * 4, h->io_out[i], true, &d[i]));
+  const int rc = rssm_run(h, with_actor, T, B, (const float *)ds0, (const float *)db0,
+                          (const float *)dact, (const float *)deps, (float *)d[0], (float *)d[1],
+                          (float *)d[2], (float *)d[3], (float *)d[4], stream);
+  if (rc != RCU_OK) return rc;
+  CU(io.finish());
+  return RCU_OK;
+}
+
+extern "C" int rssm_unroll_host(rcu_rssm_t h, int T, int B, const float *state0,
+                                const float *belief0, const float *actions, const float *eps,
+                                float *means, float *stds, float *states, float *beliefs,
+                                void *stream) {
+  return rssm_run_host(h, false, T, B, state0, belief0, actions, eps, means, stds, states, beliefs,
+                       nullptr, stream);
+}
+
+extern "C" int rssm_unroll_actor_host(rcu_rssm_t h, int T, int B, const float *state0,
+                                      const float *belief0, const float *eps, float *means,
+                                      float *stds, float *states, float *beliefs,
+                                      float *actions_out, void *stream) {
+  return rssm_run_host(h, true, T, B, state0, belief0, nullptr, eps, means, stds, states, beliefs,
+                       actions_out, stream);
 }
 
 extern "C" int rssm_get_status(rcu_rssm_t h, void *stream) {

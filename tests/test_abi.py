@@ -65,3 +65,17 @@ def test_canonical_contiguous():
 def test_binding_rejects_host_tensors():
     with pytest.raises(ValueError):
         binding._dev(torch.zeros(3))
+
+
+def test_constants_match_header():
+    """Every RCU_* value the binding names is the header's #define."""
+    import re
+    text = open(os.path.join(ROOT, "include", "rcu.h")).read()
+    defs = {m.group(1): int(m.group(2), 0) for m in
+            re.finditer(r"#define\s+(RCU_\w+)\s+\(?(-?(?:0x[0-9a-fA-F]+|\d+))\)?", text)}
+    named = [n for n in dir(binding) if n.startswith("RCU_")]
+    assert len(named) >= 10
+    for n in named:
+        assert n in defs, f"{n} is not defined in rcu.h"
+        assert getattr(binding, n) == defs[n], n
+

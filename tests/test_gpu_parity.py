@@ -529,6 +529,129 @@ def test_rssm_actor_errors():
     m0.close()
 
 
+# ----------------------------------------------------------------------------- host-buffer entry points
+
+HOST_SPECS = [
+    wl.LSTM_T80.scaled(T=9, B=3, in_dim=20, hidden=24, h0_std=0.5, c0_std=0.5),
+    wl.GRU_3L.scaled(T=6, B=130, in_dim=72, hidden=64, layers=2),
+    wl.BILSTM_VAR.scaled(T=11, B=7, in_dim=16, hidden=40, varlen=(1, 11)),
+    wl.LSTMP_2L.scaled(T=7, B=5, in_dim=24, hidden=64, proj=16),
+]
+
+
+def _host_inputs(spec, inp, pinned):
+    def h(t, dtype=torch.float32):
+        if t is None:
+            return None
+        t = t.to(dtype).contiguous()
+        return t.pin_memory() if pinned else t.clone()
+    return h(inp["x"]), h(inp["lengths"], torch.int32), h(inp["h0"]), h(inp["c0"])
+
+
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+@pytest.mark.parametrize("spec", HOST_SPECS, ids=lambda s: s.name)
+def test_forward_host_equals_device(spec, pinned):
+    """rnn_forward_host runs the same kernels as rnn_forward: with pinned
+    buffers x is read and y written in place over the CPU-GPU link, with
+    pageable ones both are staged.  Outputs are bit-identical."""
+    inp = wl.make_rnn_inputs(spec, seed=5)
+    ref = run_gpu(spec, inp)
+    net = binding.RNN.from_spec(spec)
+    net.set_weights(inp["weights"])
+    x, L, h0, c0 = _host_inputs(spec, inp, pinned)
+    LD = spec.layers * spec.D
+
+    def out(*shape):
+        t = torch.full(shape, float("nan"))
+        return t.pin_memory() if pinned else t
+    y = out(spec.T, spec.B, spec.D * spec.Hout)
+    hn = out(LD, spec.B, spec.Hout)
+    cn = out(LD, spec.B, spec.hidden) if spec.cell == "lstm" else None
+    binding.rnn_forward_host(net.h, spec.T, spec.B, x, L, h0, c0, y, hn, cn)
+    torch.cuda.synchronize()
+    assert net.status() == 0
+    assert np.array_equal(y.numpy(), ref[0])
+    assert np.array_equal(hn.numpy(), ref[1])
+    if cn is not None:
+        assert np.array_equal(cn.numpy(), ref[2])
+    net.close()
+
+
+@pytest.mark.parametrize("chunks", [2, 3, 16])
+@pytest.mark.parametrize("spec", [HOST_SPECS[1], HOST_SPECS[0], HOST_SPECS[3],
+                                  HOST_SPECS[2]], ids=lambda s: s.name)
+def test_forward_host_chunked_equals_device(spec, chunks):
+    """The chunked host pipeline (each chunk a forward of all layers from the
+    fp32 state the previous chunk left) gives the unchunked results: exactly
+    on the bf16 path, whose GEMM rows do not depend on the chunk size, and to
+    fp32 rounding on the fp32 path.  Bidirectional, varlen and projected
+    networks take the unchunked path whatever the attribute says."""
+    spec = spec.scaled(T=11) if spec.varlen is None else spec
+    inp = wl.make_rnn_inputs(spec, seed=6)
+    ref = run_gpu(spec, inp)
+    net = binding.RNN.from_spec(spec)
+    net.set_attr(binding.RCU_ATTR_HOST_CHUNKS, chunks)
+    net.set_weights(inp["weights"])
+    x, L, h0, c0 = _host_inputs(spec, inp, True)
+    LD = spec.layers * spec.D
+    y = torch.full((spec.T, spec.B, spec.D * spec.Hout), float("nan")).pin_memory()
+    hn = torch.full((LD, spec.B, spec.Hout), float("nan")).pin_memory()
+    cn = torch.full((LD, spec.B, spec.hidden), float("nan")).pin_memory() \
+        if spec.cell == "lstm" else None
+    binding.rnn_forward_host(net.h, spec.T, spec.B, x, L, h0, c0, y, hn, cn)
+    torch.cuda.synchronize()
+    assert net.status() == 0
+    got = [y.numpy(), hn.numpy()] + ([cn.numpy()] if cn is not None else [])
+    for g, r in zip(got, ref):
+        if spec.dtype == "bf16":
+            assert np.array_equal(g, r)
+        else:
+            assert np.abs(g - r).max() <= 1e-5
+    net.close()
+
+
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_rssm_host_equals_device(pinned):
+    spec = wl.RSSM_B50.scaled(T=5, B=11, state0_std=1.0, belief0_std=0.5)
+    inp = wl.make_rssm_inputs(spec, seed=9)
+    actor = wl.make_rssm_actor(spec, seed=9, actor_hidden=24)
+    dev = torch.device("cuda")
+    m = binding.RSSM(spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden)
+    m.set_weights(inp["weights"])
+    m.set_actor(actor)
+    s0, b0 = inp["state0"], inp["belief0"]
+    ref = m.unroll(inp["actions"].to(dev), inp["eps"].to(dev), s0.to(dev), b0.to(dev))
+    ref_a = m.unroll_actor(inp["eps"].to(dev), s0.to(dev), b0.to(dev))
+
+    def out(w):
+        t = torch.full((spec.T, spec.B, w), float("nan"))
+        return t.pin_memory() if pinned else t
+    S, RH, A = spec.state_dim, spec.rnn_hidden, spec.action_dim
+    got = [out(S), out(S), out(S), out(RH)]
+    binding.rssm_unroll_host(m.h, spec.T, spec.B, s0, b0, inp["actions"], inp["eps"], *got)
+    got_a = [out(S), out(S), out(S), out(RH), out(A)]
+    binding.rssm_unroll_actor_host(m.h, spec.T, spec.B, s0, b0, inp["eps"], *got_a)
+    torch.cuda.synchronize()
+    assert binding.rssm_get_status(m.h) == 0
+    for g, r in zip(got, ref):
+        assert torch.equal(g, r.cpu())
+    for g, r in zip(got_a, ref_a):
+        assert torch.equal(g, r.cpu())
+    m.close()
+
+
+def test_forward_host_rejects_device_tensors():
+    spec = HOST_SPECS[0]
+    inp = wl.make_rnn_inputs(spec, seed=5)
+    net = binding.RNN.from_spec(spec)
+    net.set_weights(inp["weights"])
+    y = torch.empty((spec.T, spec.B, spec.Hout))
+    with pytest.raises(ValueError, match="host tensors"):
+        binding.rnn_forward_host(net.h, spec.T, spec.B, inp["x"].cuda(), None, None, None, y,
+                                 None, None)
+    net.close()
+
+
 # ----------------------------------------------------------------------------- full-size workloads
 
 FULL = [
