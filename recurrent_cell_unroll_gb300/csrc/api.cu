@@ -824,12 +824,25 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
 // per-layer state carried in fp32 device buffers: the results are the
 // unchunked ones.  Copy stream cp_in moves x chunk c+2 in while chunk c+1
 // computes, cp_out moves y chunk c out meanwhile; only the first chunk's x
-// and the last chunk's y are not hidden behind compute.
+// and the last chunk's y are not hidden behind compute, so those two chunks
+// are a quarter of the others' length.
 static int forward_host_chunked(rcu_rnn_t h, int T, int B, int n, const float *x,
                                 const float *h0, const float *c0, float *y, float *h_n,
                                 float *c_n, cudaStream_t s) {
-  const int Tc = ceil_div(T, n);
-  n = ceil_div(T, Tc);
+  // chunk starts: q, then n-2 equal chunks, then q steps (q = a quarter chunk)
+  int t_at[RCU_MAX_HOST_CHUNKS + 1];
+  {
+    const int q = n >= 3 ? std::max(1, T / (4 * (n - 2) + 2)) : 0;
+    const int mid = n >= 3 ? n - 2 : n, span = T - 2 * q;
+    t_at[0] = 0;
+    int c = 0;
+    if (q > 0) t_at[++c] = q;
+    for (int i = 1; i <= mid; ++i) t_at[++c] = q + (int)((long long)span * i / mid);
+    if (q > 0) t_at[++c] = T;
+    n = c;
+  }
+  int Tc = 0;
+  for (int c = 0; c < n; ++c) Tc = std::max(Tc, t_at[c + 1] - t_at[c]);
   const size_t in_row = (size_t)B * h->in_dim, out_row = (size_t)B * h->D * h->Hout;
   const size_t LDB = (size_t)h->layers * h->D * B;
   const bool lstm = h->cell == RCU_LSTM;
@@ -856,9 +869,9 @@ static int forward_host_chunked(rcu_rnn_t h, int T, int B, int n, const float *x
   CU(cudaEventRecord(ev_entry, s));
   CU(cudaStreamWaitEvent(h->cp_in, ev_entry, 0));
   CU(cudaStreamWaitEvent(h->cp_out, ev_entry, 0));
-  auto steps_of = [&](int c) { return std::min(Tc, T - c * Tc); };
+  auto steps_of = [&](int c) { return t_at[c + 1] - t_at[c]; };
   auto copy_in = [&](int c) -> cudaError_t {
-    cudaError_t e = cudaMemcpyAsync(h->io_xc[c & 1].p, x + (size_t)c * Tc * in_row,
+    cudaError_t e = cudaMemcpyAsync(h->io_xc[c & 1].p, x + (size_t)t_at[c] * in_row,
                                     (size_t)steps_of(c) * in_row * 4, cudaMemcpyDefault,
                                     h->cp_in);
     return e != cudaSuccess ? e : cudaEventRecord(ev_in[c], h->cp_in);
@@ -878,7 +891,7 @@ static int forward_host_chunked(rcu_rnn_t h, int T, int B, int n, const float *x
     launches += h->launches;
     CU(cudaEventRecord(ev_comp[c], s));
     CU(cudaStreamWaitEvent(h->cp_out, ev_comp[c], 0));
-    CU(cudaMemcpyAsync(y + (size_t)c * Tc * out_row, h->io_yc[k].p,
+    CU(cudaMemcpyAsync(y + (size_t)t_at[c] * out_row, h->io_yc[k].p,
                        (size_t)steps_of(c) * out_row * 4, cudaMemcpyDefault, h->cp_out));
     CU(cudaEventRecord(ev_out[c], h->cp_out));
     if (c + 2 < n) {  // x buffer k is free once chunk c has computed
