@@ -376,24 +376,33 @@ def run_ours(args, spec, rank, local, ws):
 
     # ---- end to end: the library's host-buffer entry point on pinned host
     #      inputs and outputs (every byte crosses the CPU-GPU link each step)
-    host_in, host_out, host_call = e2e_io()
-    h2d = sum(v.numel() * v.element_size() for v in host_in)
-    d2h = sum(o.numel() * o.element_size() for o in host_out)
-    e2e_steps = max(1, min(args.steps, args.e2e_steps))
-    for it in range(e2e_steps + 1):
-        if it == 1:
-            dist_barrier()
-            torch.cuda.synchronize(dev)
-            ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            ea.record(stream)
-        host_call()
-    eb.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = dist_max(ea.elapsed_time(eb) / e2e_steps, dev)
-    e2e_value = dist_sum(units(spec, inp), dev) / (e2e_ms / 1e3)
-    st = status()
-    if st != 0:
-        raise RuntimeError(f"device status {st} in the end-to-end loop")
+    #      (--e2e-steps 0 skips it, e.g. for a profiler's launch list of the
+    #      timed region alone)
+    e2e = None
+    if args.e2e_steps > 0:
+        host_in, host_out, host_call = e2e_io()
+        h2d = sum(v.numel() * v.element_size() for v in host_in)
+        d2h = sum(o.numel() * o.element_size() for o in host_out)
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+        for it in range(e2e_steps + 1):
+            if it == 1:
+                dist_barrier()
+                torch.cuda.synchronize(dev)
+                ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                ea.record(stream)
+            host_call()
+        eb.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = dist_max(ea.elapsed_time(eb) / e2e_steps, dev)
+        e2e_value = dist_sum(units(spec, inp), dev) / (e2e_ms / 1e3)
+        st = status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} in the end-to-end loop")
+        e2e = {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+               "call": ("rssm_unroll_actor_host" if getattr(spec, "actor_hidden", 0) else
+                        "rssm_unroll_host") if isinstance(spec, wl.RssmSpec) else
+               "rnn_forward_host", "host_buffers": "pinned"}
 
     peaks = load_peaks()
     extra = {}
@@ -413,11 +422,7 @@ def run_ours(args, spec, rank, local, ws):
         "path_roofline": path_roofline(spec, inp, peaks, nsm, max_ms / args.steps),
         "kernels": {k: {"ms_total": round(v[0], 3), "launches": v[1]} for k, v in prof.items()}
         if prof else None,
-        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-                "call": ("rssm_unroll_actor_host" if getattr(spec, "actor_hidden", 0) else
-                         "rssm_unroll_host") if isinstance(spec, wl.RssmSpec) else
-                "rnn_forward_host", "host_buffers": "pinned"},
+        "e2e": e2e,
         "gpu_launches": n_launch,
         "clocks": clk,
         "wall_s_timed_region": round(wall, 3),
@@ -577,7 +582,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gru", choices=sorted(WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=3,
+                    help="steps of the host-buffer end-to-end leg (0 = skip it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--T", type=int, default=0,
