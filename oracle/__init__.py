@@ -64,6 +64,8 @@ def _load():
             lib.oracle_rssm_unroll2.restype = i
             lib.oracle_rssm_unroll2.argtypes = ([i, i, i, i, i, i] + [P] * 14 + [P, P, P, P, P, i, i]
                                                 + [i, P, P, P, P, P])
+            lib.oracle_rnn_backward.restype = i
+            lib.oracle_rnn_backward.argtypes = [i, i, i, i, i, i] + [P] * 14 + [i]
             lib.oracle_bf16_round.restype = ctypes.c_double
             lib.oracle_bf16_round.argtypes = [ctypes.c_float]
             lib.oracle_num_threads_default.restype = i
@@ -164,6 +166,52 @@ def rnn_forward(cell: int, x, weights, *, hidden: int, proj: int = 0, bidirectio
     if rc != 0:
         raise ValueError("oracle_rnn_forward: invalid arguments")
     return y, hn, (cn if cell == LSTM else None)
+
+
+def rnn_backward(cell: int, x, weights, dy, *, hidden: int, h0=None, c0=None, dh_n=None,
+                 dc_n=None, threads: int = 0):
+    """Backward pass through time of a stacked unidirectional LSTM / GRU
+    (no projection, lengths or clipping) in fp64: the gradients of a loss
+    with dL/dy = dy [T,B,H] (and dL/dh_n, dL/dc_n [L,B,H], None = 0).
+
+    weights: list over layers of dicts w_ih, w_hh, b_ih, b_hh (None = zero).
+    Returns a dict: dx [T,B,in], dh0 [L,B,H], dc0 [L,B,H] (LSTM, else None),
+    and per-layer lists dw_ih, dw_hh, db_ih, db_hh in the weights' shapes.
+    """
+    lib = _load()
+    x = _f32(x)
+    T, B, in_dim = x.shape
+    L = len(weights)
+    H = hidden
+    nG = 4 if cell == LSTM else 3
+    keep = []
+    arr = (_LayerW * L)()
+    for i, w in enumerate(weights):
+        vals = [_f32(w.get(k)) for k in ("w_ih", "w_hh", "b_ih", "b_hh")] + [None]
+        keep.extend(vals)
+        arr[i] = _LayerW(*[_ptr(v) for v in vals])
+    h0a, c0a, dya, dhn, dcn = _f32(h0), _f32(c0), _f32(dy), _f32(dh_n), _f32(dc_n)
+    in_l = [in_dim] + [H] * (L - 1)
+    dx = np.zeros((T, B, in_dim))
+    dh0 = np.zeros((L, B, H))
+    dc0 = np.zeros((L, B, H))
+    dwih = np.zeros(sum(nG * H * k for k in in_l))
+    dwhh = np.zeros(L * nG * H * H)
+    dbih = np.zeros(L * nG * H)
+    dbhh = np.zeros(L * nG * H)
+    rc = lib.oracle_rnn_backward(int(cell), L, in_dim, H, T, B, _ptr(x), _ptr(h0a), _ptr(c0a),
+                                 ctypes.addressof(arr), _ptr(dya), _ptr(dhn), _ptr(dcn),
+                                 _ptr(dx), _ptr(dh0), _ptr(dc0), _ptr(dwih), _ptr(dwhh),
+                                 _ptr(dbih), _ptr(dbhh), int(threads))
+    if rc != 0:
+        raise ValueError("oracle_rnn_backward: invalid arguments")
+    offs = np.cumsum([0] + [nG * H * k for k in in_l])
+    return {"dx": dx, "dh0": dh0, "dc0": dc0 if cell == LSTM else None,
+            "dw_ih": [dwih[offs[l]:offs[l + 1]].reshape(nG * H, in_l[l]) for l in range(L)],
+            "dw_hh": [dwhh[l * nG * H * H:(l + 1) * nG * H * H].reshape(nG * H, H)
+                      for l in range(L)],
+            "db_ih": [dbih[l * nG * H:(l + 1) * nG * H] for l in range(L)],
+            "db_hh": [dbhh[l * nG * H:(l + 1) * nG * H] for l in range(L)]}
 
 
 def rssm_unroll(weights, actions, eps, *, state0=None, belief0=None, rows=None, threads: int = 0):

@@ -679,3 +679,99 @@ def test_workload_generators_are_seeded():
     b = wl.make_rnn_inputs(wl.BILSTM_VAR.scaled(T=20, B=5, in_dim=4, hidden=3, varlen=(2, 20)), 0)
     assert torch.equal(a["x"], b["x"]) and torch.equal(a["lengths"], b["lengths"])
     assert int(a["lengths"].min()) >= 2 and int(a["lengths"].max()) <= 20
+
+
+# --------------------------------------------------------------------------- backward (BPTT)
+
+def _bptt_case(cell, layers, seed, T=5, B=3, in_dim=4, H=3):
+    rng = np.random.default_rng(seed)
+    ws = _rand_weights(rng, cell, layers, in_dim, H)
+    x = rng.standard_normal((T, B, in_dim)).astype(np.float32)
+    h0 = (0.5 * rng.standard_normal((layers, B, H))).astype(np.float32)
+    c0 = (0.5 * rng.standard_normal((layers, B, H))).astype(np.float32)
+    dy = rng.standard_normal((T, B, H)).astype(np.float32)
+    dhn = rng.standard_normal((layers, B, H)).astype(np.float32)
+    dcn = rng.standard_normal((layers, B, H)).astype(np.float32)
+    if cell == oracle.GRU:
+        c0 = dcn = None
+    return ws, x, h0, c0, dy, dhn, dcn
+
+
+@pytest.mark.parametrize("cell,layers", [(oracle.LSTM, 1), (oracle.LSTM, 3), (oracle.GRU, 1),
+                                         (oracle.GRU, 2)])
+def test_bptt_against_torch_autograd(cell, layers):
+    """The oracle's gradients equal torch float64 autograd through nn.LSTM /
+    nn.GRU (a library routine) for loss = <y, dy> + <h_n, dh_n> (+ <c_n, dc_n>)."""
+    ws, x, h0, c0, dy, dhn, dcn = _bptt_case(cell, layers, seed=10 + layers + 5 * cell)
+    T, B, in_dim = x.shape
+    H = 3
+    g = oracle.rnn_backward(cell, x, ws, dy, hidden=H, h0=h0, c0=c0, dh_n=dhn, dc_n=dcn)
+    kw = dict(input_size=in_dim, hidden_size=H, num_layers=layers, dtype=torch.float64)
+    mod = torch.nn.LSTM(**kw) if cell == oracle.LSTM else torch.nn.GRU(**kw)
+    with torch.no_grad():
+        for layer in range(layers):
+            for k, name in (("w_ih", "weight_ih"), ("w_hh", "weight_hh"), ("b_ih", "bias_ih"),
+                            ("b_hh", "bias_hh")):
+                getattr(mod, f"{name}_l{layer}").copy_(torch.from_numpy(ws[layer][k]).double())
+    xt = torch.from_numpy(x).double().requires_grad_()
+    ht = torch.from_numpy(h0).double().requires_grad_()
+    if cell == oracle.LSTM:
+        ct = torch.from_numpy(c0).double().requires_grad_()
+        y, (hn, cn) = mod(xt, (ht, ct))
+        loss = (y * torch.from_numpy(dy).double()).sum() + \
+            (hn * torch.from_numpy(dhn).double()).sum() + (cn * torch.from_numpy(dcn).double()).sum()
+    else:
+        y, hn = mod(xt, ht)
+        loss = (y * torch.from_numpy(dy).double()).sum() + (hn * torch.from_numpy(dhn).double()).sum()
+    loss.backward()
+    tol = dict(rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(g["dx"], xt.grad.numpy(), **tol)
+    np.testing.assert_allclose(g["dh0"], ht.grad.numpy(), **tol)
+    if cell == oracle.LSTM:
+        np.testing.assert_allclose(g["dc0"], ct.grad.numpy(), **tol)
+    for layer in range(layers):
+        for k, name in (("dw_ih", "weight_ih"), ("dw_hh", "weight_hh"), ("db_ih", "bias_ih"),
+                        ("db_hh", "bias_hh")):
+            np.testing.assert_allclose(g[k][layer], getattr(mod, f"{name}_l{layer}").grad.numpy(),
+                                       **tol, err_msg=f"{k} layer {layer}")
+
+
+@pytest.mark.parametrize("cell", [oracle.LSTM, oracle.GRU])
+def test_bptt_finite_differences(cell):
+    """Central differences of the (separately pinned) oracle forward agree with
+    the oracle's backward, for entries of x, h0, c0 and every weight tensor."""
+    layers = 2
+    ws, x, h0, c0, dy, dhn, dcn = _bptt_case(cell, layers, seed=77 + cell, T=4, B=2)
+    H = 3
+
+    def loss(x_, ws_, h0_, c0_):
+        y, hn, cn = oracle.rnn_forward(cell, x_, ws_, hidden=H, h0=h0_, c0=c0_)
+        v = float((y * dy).sum() + (hn * dhn).sum())
+        if cell == oracle.LSTM:
+            v += float((cn * dcn).sum())
+        return v
+
+    g = oracle.rnn_backward(cell, x, ws, dy, hidden=H, h0=h0, c0=c0, dh_n=dhn, dc_n=dcn)
+    eps = np.float32(2.0 ** -10)   # exact in fp32 at these magnitudes
+    rng = np.random.default_rng(5)
+
+    def check(arr, grad, rebuild):
+        for _ in range(4):
+            idx = tuple(int(rng.integers(0, n)) for n in arr.shape)
+            hi, lo = arr.copy(), arr.copy()
+            hi[idx] += eps
+            lo[idx] -= eps
+            fd = (loss(*rebuild(hi)) - loss(*rebuild(lo))) / (2 * float(eps))
+            assert abs(fd - grad[idx]) <= 1e-5 * max(1.0, abs(grad[idx])), (idx, fd, grad[idx])
+
+    check(x, g["dx"], lambda a: (a, ws, h0, c0))
+    check(h0, g["dh0"], lambda a: (x, ws, a, c0))
+    if cell == oracle.LSTM:
+        check(c0, g["dc0"], lambda a: (x, ws, h0, a))
+    for layer in range(layers):
+        for k, gk in (("w_ih", "dw_ih"), ("w_hh", "dw_hh"), ("b_ih", "db_ih"), ("b_hh", "db_hh")):
+            def rebuild(a, layer=layer, k=k):
+                w2 = [dict(w) for w in ws]
+                w2[layer][k] = a
+                return x, w2, h0, c0
+            check(ws[layer][k], g[gk][layer], rebuild)
