@@ -192,6 +192,34 @@ RCU_API int rnn_forward_host(rcu_rnn_t h, int T, int B, const float *x, const in
                              void *stream);
 
 /*
+ * Backward pass through time (BPTT), the training use of the unrolled cell
+ * ("[Feature Request] CUDNN version of RSSM", pytorch/rl issue 366,
+ * Motivation; "Integrating CuDNN API for LSTMs with projections",
+ * pytorch/pytorch issue 46213, training discussion).  fp32 handles,
+ * unidirectional, without projection, lengths or clipping (else
+ * RCU_ERR_UNSUPPORTED).  Given the forward's inputs x [T,B,in], h0 / c0
+ * ([L,B,H] or NULL) and the gradient of a loss with respect to y, dy
+ * [T,B,H] (and to h_n / c_n, dh_n / dc_n [L,B,H] or NULL = 0), writes the
+ * gradients dx [T,B,in], dh0 [L,B,H] and dc0 [L,B,H] (LSTM) — each may be
+ * NULL — and keeps the weight gradients of every layer, summed over rows and
+ * steps, for rnn_get_weight_grads.  All device pointers; asynchronous on
+ * `stream`; a device-side failure is reported by rnn_get_status.
+ * The forward is recomputed inside the call (every layer's output sequence
+ * is kept), so only dh_{t-1} = W_hh^T dz_t runs step by step; the rest are
+ * GEMMs over all T*B rows.
+ */
+RCU_API int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const float *h0,
+                         const float *c0, const float *dy, const float *dh_n, const float *dc_n,
+                         float *dx, float *dh0, float *dc0, void *stream);
+/*
+ * Weight gradients of layer `layer` (dir 0) from the last rnn_backward, in the
+ * weights' own layout: dW_ih [nG*H, in_l], dW_hh [nG*H, H], db_ih, db_hh
+ * [nG*H] (any of them may be NULL).  RCU_ERR_STATE before any rnn_backward.
+ */
+RCU_API int rnn_get_weight_grads(rcu_rnn_t h, int layer, int dir, float *dW_ih, float *dW_hh,
+                                 float *db_ih, float *db_hh, void *stream);
+
+/*
  * Copy the packing metadata of the last rnn_forward (device int32 buffers):
  *   sorted_idx[B]   original row at sorted position s (length descending,
  *                   equal lengths in ascending row order),

@@ -39,7 +39,7 @@ EXPORTED = (
     "rssm_create", "rssm_set_weights", "rssm_unroll", "rssm_get_status",
     "rssm_last_launch_count", "rssm_destroy", "rssm_set_attr", "rssm_get_trace",
     "rssm_set_actor", "rssm_unroll_actor", "rnn_forward_host", "rssm_unroll_host",
-    "rssm_unroll_actor_host",
+    "rssm_unroll_actor_host", "rnn_backward", "rnn_get_weight_grads",
 )
 
 _lib = None
@@ -96,6 +96,8 @@ def load(path: Optional[str] = None):
             "rssm_set_actor": (I, [P, I, P, P, P, P, P]),
             "rssm_unroll_actor": (I, [P, I, I] + [P] * 8 + [P]),
             "rnn_forward_host": (I, [P, I, I] + [P] * 8),
+            "rnn_backward": (I, [P, I, I] + [P] * 10),
+            "rnn_get_weight_grads": (I, [P, I, I, P, P, P, P, P]),
             "rssm_unroll_host": (I, [P, I, I] + [P] * 8 + [P]),
             "rssm_unroll_actor_host": (I, [P, I, I] + [P] * 8 + [P]),
         }
@@ -258,6 +260,19 @@ def rnn_forward_host(h, T: int, B: int, x, lengths, h0, c0, y, h_n, c_n, stream=
                                    _stream(stream)))
 
 
+def rnn_backward(h, T: int, B: int, x, h0, c0, dy, dh_n, dc_n, dx, dh0, dc0, stream=None):
+    """Backward pass through time (see rcu.h); device tensors."""
+    ins = [_dev(t) for t in (x, h0, c0, dy, dh_n, dc_n)]
+    outs = [_dev(t) for t in (dx, dh0, dc0)]
+    _check(load().rnn_backward(h, T, B, *[k[1] for k in ins], *[k[1] for k in outs],
+                               _stream(stream)))
+
+
+def rnn_get_weight_grads(h, layer: int, dW_ih, dW_hh, db_ih, db_hh, stream=None):
+    outs = [_dev(t) for t in (dW_ih, dW_hh, db_ih, db_hh)]
+    _check(load().rnn_get_weight_grads(h, layer, 0, *[k[1] for k in outs], _stream(stream)))
+
+
 def rssm_create(state_dim: int, action_dim: int, hidden: int, rnn_hidden: int):
     h = ctypes.c_void_p()
     _check(load().rssm_create(ctypes.byref(h), state_dim, action_dim, hidden, rnn_hidden))
@@ -366,6 +381,28 @@ class RNN:
             if self.cell == "lstm" else None
         rnn_forward(self.h, T, B, x, lengths, h0, c0, None, y, hn, cn, stream)
         return y, hn, cn
+
+    def backward(self, x, dy, h0=None, c0=None, dh_n=None, dc_n=None, stream=None):
+        """Gradients of a loss with dL/dy = dy (and dL/dh_n, dL/dc_n) through
+        the forward on x: returns (dx, dh0, dc0 or None, weight grads as a
+        list over layers of dicts w_ih, w_hh, b_ih, b_hh)."""
+        T, B, in_dim = x.shape
+        dev = x.device
+        dx = torch.empty_like(x)
+        dh0 = torch.empty((self.layers, B, self.hidden), device=dev)
+        dc0 = torch.empty_like(dh0) if self.cell == "lstm" else None
+        rnn_backward(self.h, T, B, x, h0, c0, dy, dh_n, dc_n, dx, dh0, dc0, stream)
+        nG = 4 if self.cell == "lstm" else 3
+        grads = []
+        for layer in range(self.layers):
+            k = in_dim if layer == 0 else self.hidden
+            g = {"w_ih": torch.empty((nG * self.hidden, k), device=dev),
+                 "w_hh": torch.empty((nG * self.hidden, self.hidden), device=dev),
+                 "b_ih": torch.empty((nG * self.hidden,), device=dev),
+                 "b_hh": torch.empty((nG * self.hidden,), device=dev)}
+            rnn_get_weight_grads(self.h, layer, g["w_ih"], g["w_hh"], g["b_ih"], g["b_hh"], stream)
+            grads.append(g)
+        return dx, dh0, dc0, grads
 
     def status(self, stream=None) -> int:
         return rnn_get_status(self.h, stream)

@@ -169,6 +169,9 @@ struct LayerDirW {
   // bf16 LSTMP tensor-core path: packed W_hh W_hr, fp32 copy of the rounded
   // W_hh (initial-state term) and bf16 W_hr [P][round_up(H, 8)] (projection GEMM)
   DevBuf fold_w, whh_f32, whr_bf;
+  // fp32 handles without projection: plain W_hh [nG*H][round_up(H, 8)], b_ih,
+  // b_hh (zeros when NULL) for the backward pass
+  DevBuf whh_plain, bih_plain, bhh_plain;
   bool set = false;
 };
 
@@ -212,6 +215,12 @@ struct rcu_rnn_s {
   cudaStream_t cp_in = nullptr, cp_out = nullptr;
   std::vector<cudaEvent_t> chunk_ev;
   DevBuf io_xc[2], io_yc[2], io_st[2], io_ct[2];
+  // rnn_backward: workspace, per-layer weight gradients of the last call, and
+  // the forward's per-layer outputs (layer l < L-1 written to keep_out + l*T*B*Hout)
+  DevBuf bw;
+  std::vector<DevBuf> gw;
+  bool grads_ready = false;
+  float *keep_out = nullptr;
   // opt-in per-step trace of the first layer's recurrent kernel
   bool trace = false;
   DevBuf trace_buf;
@@ -522,6 +531,16 @@ extern "C" int rnn_set_weights(rcu_rnn_t h, int layer, int dir, const float *W_i
       for (int k = 0; k < H; ++k) hr[(size_t)q * ldH + k] = f2bf(whr[(size_t)q * H + k]);
     CU(lw.whr_bf.upload(hr.data(), hr.size() * 2));
   }
+  // --- plain fp32 copies for the backward pass
+  if (!bf && P == 0) {
+    const int ldh = round_up(H, 8);
+    std::vector<float> wp((size_t)nG * H * ldh, 0.f);
+    for (int r = 0; r < nG * H; ++r)
+      for (int k = 0; k < H; ++k) wp[(size_t)r * ldh + k] = whh[(size_t)r * Hout + k];
+    CU(lw.whh_plain.upload(wp.data(), wp.size() * 4));
+    CU(lw.bih_plain.upload(bih.data(), (size_t)nG * H * 4));
+    CU(lw.bhh_plain.upload(bhh.data(), (size_t)nG * H * 4));
+  }
   lw.set = true;
   return RCU_OK;
 }
@@ -690,7 +709,7 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
     p.c0 = c0 ? c0 + (size_t)l * D * B * H : nullptr;
     p.h_n = h_n ? h_n + (size_t)l * D * B * Hout : nullptr;
     p.c_n = c_n ? c_n + (size_t)l * D * B * H : nullptr;
-    p.y = last ? y : nullptr;
+    p.y = last ? y : (h->keep_out ? h->keep_out + (size_t)l * T * B * D * Hout : nullptr);
     p.ymid = last ? nullptr : h->ymid;
     p.hx = h->hx; p.mx = h->mx; p.hst = h->hst; p.cst = h->cst;
     p.ctr = ctr + (size_t)cstride * l;  // fresh counters per layer (zeroed above)
@@ -952,6 +971,147 @@ extern "C" int rnn_forward_host(rcu_rnn_t h, int T, int B, const float *x, const
   h->x_in_place = false;
   if (rc != RCU_OK) return rc;
   CU(io.finish());
+  return RCU_OK;
+}
+
+// Backward pass through time (fp32 handles, unidirectional, no projection,
+// lengths or clipping).  Recompute design: the forward is run again keeping
+// every layer's output, which makes all of h_{t-1} known, so the layer's
+// pre-activations are two GEMMs over all steps and the LSTM cell sequence one
+// elementwise scan; only dh_{t-1} = W_hh^T dR_t runs step by step
+// (bwd_rec_kernel).  Weight and input gradients are GEMMs over all T*B rows.
+extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const float *h0,
+                            const float *c0, const float *dy, const float *dh_n,
+                            const float *dc_n, float *dx, float *dh0, float *dc0, void *stream) {
+  if (!h) return fail(RCU_ERR_INVALID, "rnn_backward: NULL handle");
+  h->launches = 0;
+  for (auto &w : h->lw)
+    if (!w.set) return fail(RCU_ERR_STATE, "rnn_backward: weights missing for some layer/direction");
+  if (h->dtype != RCU_F32 || h->D != 1 || h->P != 0 || h->cclip || h->pclip)
+    return fail(RCU_ERR_UNSUPPORTED,
+                "rnn_backward: fp32 unidirectional networks without projection or clipping");
+  if (T < 1 || B < 1 || !x || !dy) return fail(RCU_ERR_INVALID, "rnn_backward: need T, B >= 1, x and dy");
+  if (h->cell == RCU_GRU && (c0 || dc_n || dc0))
+    return fail(RCU_ERR_INVALID, "rnn_backward: c0/dc_n/dc0 are LSTM-only");
+  if ((size_t)T * B > (size_t)INT32_MAX / 8)
+    return fail(RCU_ERR_UNSUPPORTED, "rnn_backward: T*B too large");
+  const int L = h->layers, H = h->H, nG = h->nG, G = nG * H, cell = h->cell;
+  if (bwd_units_per_cta(H, B, nG, h->nsm) < 1)
+    return fail(RCU_ERR_UNSUPPORTED, "rnn_backward: W_hh columns do not fit one SM per unit group");
+  cudaStream_t s = (cudaStream_t)stream;
+  const int M = T * B;
+  const size_t TBH = (size_t)M * H, TBG = (size_t)M * G;
+  int kmax = H;
+  for (int l = 0; l < L; ++l) kmax = std::max(kmax, h->in_l[l]);
+  // ---- workspace (floats; every piece 256-byte aligned)
+  size_t off = 0;
+  auto take = [&](size_t n) { size_t r = off; off += (n + 63) & ~size_t(63); return r; };
+  const size_t o_keep = take((size_t)L * TBH), o_hp = take(TBH), o_zin = take(TBG),
+               o_zh = take(TBG), o_cs = take(cell == RCU_LSTM ? TBH : 0), o_da = take(TBG),
+               o_dr = take(cell == RCU_GRU ? TBG : 0), o_dya = take(TBH), o_dyb = take(TBH),
+               o_t1 = take(TBG), o_t2 = take((size_t)M * kmax), o_wt = take((size_t)kmax * G),
+               o_cs2 = take(colsum_scratch_floats(M, G)), o_ctl = take(64);
+  CU(h->bw.ensure(off * 4));
+  float *wsf = (float *)h->bw.p;
+  float *keep = wsf + o_keep, *hp = wsf + o_hp, *zin = wsf + o_zin, *zh = wsf + o_zh;
+  float *cs = cell == RCU_LSTM ? wsf + o_cs : nullptr, *DA = wsf + o_da;
+  float *DR = cell == RCU_GRU ? wsf + o_dr : DA;
+  float *dYa = wsf + o_dya, *dYb = wsf + o_dyb, *T1 = wsf + o_t1, *T2 = wsf + o_t2;
+  float *WT = wsf + o_wt, *csum = wsf + o_cs2;
+  unsigned *ctr = (unsigned *)(wsf + o_ctl);
+  if ((int)h->gw.size() < L) h->gw.resize(L);
+  h->grads_ready = false;
+  int launches = 0;
+  // ---- forward again, keeping every layer's output sequence
+  h->keep_out = keep;
+  int rc = rnn_forward(h, T, B, x, nullptr, h0, c0, nullptr, keep + (size_t)(L - 1) * TBH,
+                       nullptr, nullptr, stream);
+  h->keep_out = nullptr;
+  if (rc != RCU_OK) return rc;
+  launches += h->launches;
+  // the handle's error word (cleared by the forward above), read by rnn_get_status
+  int *err = (int *)h->ctl.p;
+  const float *dYcur = dy;
+  for (int l = L - 1; l >= 0; --l) {
+    const int K = h->in_l[l], ldk = round_up(K, 8), ldh = round_up(H, 8);
+    const LayerDirW &lw = h->lw[(size_t)l];
+    const float *X = l == 0 ? x : keep + (size_t)(l - 1) * TBH;
+    float *dX = l == 0 ? dx : (dYcur == dYa ? dYb : dYa);
+    // h_{t-1} for t = 0 .. T-1
+    if (h0) CU(cudaMemcpyAsync(hp, h0 + (size_t)l * B * H, (size_t)B * H * 4, cudaMemcpyDeviceToDevice, s));
+    else CU(cudaMemsetAsync(hp, 0, (size_t)B * H * 4, s));
+    if (T > 1)
+      CU(cudaMemcpyAsync(hp + (size_t)B * H, keep + (size_t)l * TBH, (size_t)(T - 1) * B * H * 4,
+                         cudaMemcpyDeviceToDevice, s));
+    // pre-activations of every step
+    cudaError_t e = launch_gemm_simt<float, float>(X, K, (const float *)h->wih[l].p, ldk,
+                                                   (const float *)lw.bih_plain.p, zin, G, M,
+                                                   nullptr, G, K, s, err);
+    if (e == cudaSuccess)
+      e = launch_gemm_simt<float, float>(hp, H, (const float *)lw.whh_plain.p, ldh,
+                                         (const float *)lw.bhh_plain.p, zh, G, M, nullptr, G, H,
+                                         s, err);
+    const float *c0l = c0 ? c0 + (size_t)l * B * H : nullptr;
+    if (e == cudaSuccess) e = launch_bwd_prep(T, B, H, cell, zin, zh, c0l, cs, s);
+    if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: recompute: %s", cudaGetErrorString(e));
+    // the reverse-time recurrence
+    CU(cudaMemsetAsync(ctr, 0, 16 * 4, s));
+    BwdRecArgs a{};
+    a.T = T; a.B = B; a.H = H; a.cell = cell;
+    a.Whh = (const float *)lw.whh_plain.p; a.ldw = ldh;
+    a.gates = zin; a.zh = zh; a.cs = cs; a.c0 = c0l; a.hp = hp; a.dy = dYcur;
+    a.dhn = dh_n ? dh_n + (size_t)l * B * H : nullptr;
+    a.dcn = dc_n ? dc_n + (size_t)l * B * H : nullptr;
+    a.DA = DA; a.DR = DR;
+    a.dh0 = dh0 ? dh0 + (size_t)l * B * H : nullptr;
+    a.dc0 = dc0 ? dc0 + (size_t)l * B * H : nullptr;
+    a.ctr = ctr; a.err = err; a.timeout_ns = (uint64_t)h->timeout_ns;
+    e = launch_bwd_rec(a, h->nsm, s);
+    if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: recurrence: %s", cudaGetErrorString(e));
+    // weight gradients: dW_ih = DA^T X, dW_hh = DR^T H_prev, db = column sums
+    DevBuf &g = h->gw[l];
+    CU(g.ensure(((size_t)G * K + (size_t)G * H + 2 * (size_t)G) * 4));
+    float *gWih = (float *)g.p, *gWhh = gWih + (size_t)G * K, *gbih = gWhh + (size_t)G * H,
+          *gbhh = gbih + G;
+    e = launch_transpose(DA, M, G, G, T1, M, s);
+    if (e == cudaSuccess) e = launch_transpose(X, M, K, K, T2, M, s);
+    if (e == cudaSuccess)
+      e = launch_gemm_simt<float, float>(T1, M, T2, M, nullptr, gWih, K, G, nullptr, K, M, s, err);
+    if (e == cudaSuccess) e = launch_transpose(DR, M, G, G, T1, M, s);
+    if (e == cudaSuccess) e = launch_transpose(hp, M, H, H, T2, M, s);
+    if (e == cudaSuccess)
+      e = launch_gemm_simt<float, float>(T1, M, T2, M, nullptr, gWhh, H, G, nullptr, H, M, s, err);
+    if (e == cudaSuccess) e = launch_colsum(DA, M, G, csum, gbih, s);
+    if (e == cudaSuccess) e = launch_colsum(DR, M, G, csum, gbhh, s);
+    // input gradient dX = DA W_ih (W_ih transposed to [K][G])
+    if (e == cudaSuccess) e = launch_transpose((const float *)h->wih[l].p, G, K, ldk, WT, G, s);
+    if (e == cudaSuccess && dX)
+      e = launch_gemm_simt<float, float>(DA, G, WT, G, nullptr, dX, K, M, nullptr, K, G, s, err);
+    if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: gradients: %s", cudaGetErrorString(e));
+    launches += 16;  // 5 GEMMs, 5 transposes, prep, recurrence, 2 two-kernel column sums
+    dYcur = dX;
+    if (l > 0 && !dX) return fail(RCU_ERR_INVALID, "rnn_backward: internal");
+  }
+  h->grads_ready = true;
+  h->launches = launches;
+  return RCU_OK;
+}
+
+extern "C" int rnn_get_weight_grads(rcu_rnn_t h, int layer, int dir, float *dW_ih, float *dW_hh,
+                                    float *db_ih, float *db_hh, void *stream) {
+  if (!h) return fail(RCU_ERR_INVALID, "rnn_get_weight_grads: NULL handle");
+  if (!h->grads_ready) return fail(RCU_ERR_STATE, "rnn_get_weight_grads: no rnn_backward has run");
+  if (layer < 0 || layer >= h->layers || dir != 0)
+    return fail(RCU_ERR_INVALID, "rnn_get_weight_grads: layer %d / dir %d out of range", layer, dir);
+  cudaStream_t s = (cudaStream_t)stream;
+  const int G = h->nG * h->H, K = h->in_l[layer], H = h->H;
+  const float *g = (const float *)h->gw[layer].p;
+  const float *src[4] = {g, g + (size_t)G * K, g + (size_t)G * K + (size_t)G * H,
+                         g + (size_t)G * K + (size_t)G * H + G};
+  float *dst[4] = {dW_ih, dW_hh, db_ih, db_hh};
+  const size_t n[4] = {(size_t)G * K, (size_t)G * H, (size_t)G, (size_t)G};
+  for (int i = 0; i < 4; ++i)
+    if (dst[i]) CU(cudaMemcpyAsync(dst[i], src[i], n[i] * 4, cudaMemcpyDefault, s));
   return RCU_OK;
 }
 

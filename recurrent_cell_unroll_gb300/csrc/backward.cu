@@ -1,0 +1,269 @@
+// Backward pass through time (BPTT) of the stacked unidirectional LSTM / GRU,
+// fp32: the training use of the unrolled cell behind "[Feature Request] CUDNN
+// version of RSSM" (pytorch/rl issue 366, Motivation: the loop dominates
+// training) and "Integrating CuDNN API for LSTMs with projections"
+// (pytorch/pytorch issue 46213, the training discussion).
+//
+// The sequential part is only the recurrence of the hidden-state gradient,
+//     dh_{t-1} = W_hh^T dR_t (+ z_t * dh_t for the GRU),
+// which bwd_rec_kernel runs as one persistent cooperative launch over all
+// steps in reverse time: each CTA owns U hidden units (all batch rows) with
+// their columns of W_hh resident in shared memory, computes the gate
+// gradients of its units from the saved activations, publishes them, crosses
+// one bounded grid barrier, and forms its units' dh_{t-1} from everyone's
+// gate gradients.  Everything else is parallel over steps: the pre-activations
+// are recomputed as two GEMMs (X W_ih^T, H_prev W_hh^T) once every layer's
+// output sequence is known, the LSTM cell sequence is one elementwise scan
+// (bwd_prep_kernel), and the weight and input gradients are GEMMs over all
+// T*B rows (through transposes) plus a deterministic column sum for the
+// biases.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace rcu {
+
+namespace {
+
+constexpr int NT = 512;
+
+// ---- activations and the LSTM cell scan.  zin holds X W_ih^T + b_ih on
+// entry and the activated gates on exit (LSTM i, f, g, o; GRU r, z, n);
+// zh = H_prev W_hh^T + b_hh is only read.  cs[t][b][u] = c_t (LSTM).
+__global__ void bwd_prep_kernel(int T, int B, int H, int cell, float *__restrict__ zin,
+                                const float *__restrict__ zh, const float *__restrict__ c0,
+                                float *__restrict__ cs) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= B * H) return;
+  const int b = e / H, u = e % H;
+  const int nG = cell == CELL_LSTM ? 4 : 3, G = nG * H;
+  float c = (cell == CELL_LSTM && c0) ? c0[(size_t)b * H + u] : 0.f;
+  for (int t = 0; t < T; ++t) {
+    const size_t r = (size_t)t * B + b;
+    float *a = zin + r * G;
+    const float *h = zh + r * G;
+    if (cell == CELL_LSTM) {
+      const float i = sigmoid_f(a[u] + h[u]);
+      const float f = sigmoid_f(a[H + u] + h[H + u]);
+      const float g = tanh_f(a[2 * H + u] + h[2 * H + u]);
+      const float o = sigmoid_f(a[3 * H + u] + h[3 * H + u]);
+      c = f * c + i * g;
+      cs[r * H + u] = c;
+      a[u] = i; a[H + u] = f; a[2 * H + u] = g; a[3 * H + u] = o;
+    } else {
+      const float rg = sigmoid_f(a[u] + h[u]);
+      const float z = sigmoid_f(a[H + u] + h[H + u]);
+      const float n = tanh_f(a[2 * H + u] + rg * h[2 * H + u]);
+      a[u] = rg; a[H + u] = z; a[2 * H + u] = n;
+    }
+  }
+}
+
+struct BwdParams {
+  int T, B, H, cell, U;
+  const float *Whh;   // [nG*H][ldw], PyTorch row order
+  int ldw;
+  const float *gates; // [T*B][G] activated gates
+  const float *zh;    // GRU: [T*B][G] hidden-side pre-activations (n part: W_hn h' + b_hn)
+  const float *cs;    // LSTM: [T*B][H] c_t
+  const float *c0;    // LSTM: [B][H] or NULL
+  const float *hp;    // GRU: [T*B][H] h_{t-1}
+  const float *dy;    // [T*B][H]
+  const float *dhn, *dcn;  // [B][H] or NULL
+  float *DA, *DR;     // [T*B][G]: input-side and hidden-side gate gradients (LSTM: DR == DA)
+  float *dh0, *dc0;   // [B][H] or NULL
+  unsigned *ctr;
+  int *err;
+  uint64_t timeout_ns;
+};
+
+__global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
+  extern __shared__ __align__(16) float sm[];
+  const int H = p.H, B = p.B, U = p.U;
+  const bool lstm = p.cell == CELL_LSTM;
+  const int G = (lstm ? 4 : 3) * H;
+  const int u0 = blockIdx.x * U, nu = max(0, min(U, H - u0));
+  float *WT = sm;                        // [U][G]: WT[j][n] = W_hh[n][u0 + j]
+  float *dhrec = WT + (size_t)U * G;     // [B][U]: W_hh^T dR part of dh_t (+ direct GRU path)
+  float *dcs = dhrec + (size_t)B * U;    // [B][U]: LSTM dc carried to the previous step
+  float *dhz = dcs + (size_t)B * U;      // [B][U]: GRU z * dh (direct path)
+  const int tid = threadIdx.x;
+  for (int e = tid; e < U * G; e += NT) {
+    const int j = e / G, n = e % G;
+    WT[e] = j < nu ? p.Whh[(size_t)n * p.ldw + u0 + j] : 0.f;
+  }
+  for (int e = tid; e < B * U; e += NT) {
+    const int b = e / U, j = e % U;
+    const bool ok = j < nu;
+    dhrec[e] = (ok && p.dhn) ? p.dhn[(size_t)b * H + u0 + j] : 0.f;
+    dcs[e] = (ok && lstm && p.dcn) ? p.dcn[(size_t)b * H + u0 + j] : 0.f;
+    dhz[e] = 0.f;
+  }
+  __syncthreads();
+  const bool vec = (G & 3) == 0;
+  for (int t = p.T - 1, it = 1; t >= 0; --t, ++it) {
+    // ---- gate gradients of this CTA's units at step t
+    for (int e = tid; e < B * U; e += NT) {
+      const int b = e / U, j = e % U;
+      if (j >= nu) continue;
+      const int u = u0 + j;
+      const size_t r = (size_t)t * B + b;
+      const float dh = p.dy[r * H + u] + dhrec[e];
+      const float *g = p.gates + r * G;
+      float *da = p.DA + r * G;
+      if (lstm) {
+        const float i = g[u], f = g[H + u], gg = g[2 * H + u], o = g[3 * H + u];
+        const float c = p.cs[r * H + u];
+        const float cp = t > 0 ? p.cs[(r - B) * H + u] : (p.c0 ? p.c0[(size_t)b * H + u] : 0.f);
+        const float tc = tanh_f(c);
+        const float dc = dcs[e] + dh * o * (1.f - tc * tc);
+        da[u] = dc * gg * i * (1.f - i);
+        da[H + u] = dc * cp * f * (1.f - f);
+        da[2 * H + u] = dc * i * (1.f - gg * gg);
+        da[3 * H + u] = dh * tc * o * (1.f - o);
+        dcs[e] = dc * f;
+      } else {
+        const float rg = g[u], z = g[H + u], n = g[2 * H + u];
+        const float hn = p.zh[r * G + 2 * H + u];
+        const float hprev = p.hp[r * H + u];
+        const float dn = dh * (1.f - z);
+        const float dz = dh * (hprev - n);
+        const float dan = dn * (1.f - n * n);
+        const float ar = dan * hn * rg * (1.f - rg);
+        const float az = dz * z * (1.f - z);
+        float *dr = p.DR + r * G;
+        da[u] = ar; da[H + u] = az; da[2 * H + u] = dan;
+        dr[u] = ar; dr[H + u] = az; dr[2 * H + u] = dan * rg;
+        dhz[e] = dh * z;
+      }
+    }
+    // every CTA's gate gradients of step t are published
+    if (!group_barrier(p.ctr, (unsigned)it * gridDim.x, p.err, p.timeout_ns)) return;
+    // ---- dh_{t-1} of this CTA's units: W_hh^T dR_t (+ z dh)
+    const float *drt = (lstm ? p.DA : p.DR) + (size_t)t * B * G;
+    for (int e = tid; e < B * U; e += NT) {
+      const int b = e / U, j = e % U;
+      if (j >= nu) continue;
+      const float *v = drt + (size_t)b * G, *w = WT + (size_t)j * G;
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+      int n = 0;
+      if (vec) {
+#pragma unroll 4
+        for (; n + 3 < G; n += 4) {
+          const float4 x = __ldcg(reinterpret_cast<const float4 *>(v + n));
+          const float4 y = *reinterpret_cast<const float4 *>(w + n);
+          a0 = fmaf(x.x, y.x, a0);
+          a1 = fmaf(x.y, y.y, a1);
+          a2 = fmaf(x.z, y.z, a2);
+          a3 = fmaf(x.w, y.w, a3);
+        }
+      }
+      for (; n < G; ++n) a0 = fmaf(__ldcg(v + n), w[n], a0);
+      dhrec[e] = (lstm ? 0.f : dhz[e]) + ((a0 + a1) + (a2 + a3));
+    }
+    __syncthreads();
+  }
+  for (int e = tid; e < B * U; e += NT) {
+    const int b = e / U, j = e % U;
+    if (j >= nu) continue;
+    if (p.dh0) p.dh0[(size_t)b * H + u0 + j] = dhrec[e];
+    if (lstm && p.dc0) p.dc0[(size_t)b * H + u0 + j] = dcs[e];
+  }
+}
+
+// out[c][r] = in[r][c] for an R x C row-major matrix (ldi, ldo: row strides)
+__global__ void transpose_kernel(const float *__restrict__ in, int R, int C, int ldi,
+                                 float *__restrict__ out, int ldo) {
+  __shared__ float tile[32][33];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int r = r0 + i, c = c0 + threadIdx.x;
+    if (r < R && c < C) tile[i][threadIdx.x] = in[(size_t)r * ldi + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int c = c0 + i, r = r0 + threadIdx.x;
+    if (r < R && c < C) out[(size_t)c * ldo + r] = tile[threadIdx.x][i];
+  }
+}
+
+// deterministic column sums of an M x N row-major matrix: chunk partials,
+// then the chunks summed in order
+constexpr int CS_ROWS = 1024;
+__global__ void colsum_partial_kernel(const float *__restrict__ A, int M, int N,
+                                      float *__restrict__ part) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= N) return;
+  const int m0 = blockIdx.y * CS_ROWS, m1 = min(M, m0 + CS_ROWS);
+  float s = 0.f;
+  for (int m = m0; m < m1; ++m) s += A[(size_t)m * N + n];
+  part[(size_t)blockIdx.y * N + n] = s;
+}
+__global__ void colsum_final_kernel(const float *__restrict__ part, int chunks, int N,
+                                    float *__restrict__ out) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= N) return;
+  float s = 0.f;
+  for (int c = 0; c < chunks; ++c) s += part[(size_t)c * N + n];
+  out[n] = s;
+}
+
+size_t rec_smem(int U, int G, int B) { return ((size_t)U * G + 3 * (size_t)B * U) * sizeof(float); }
+
+}  // namespace
+
+cudaError_t launch_bwd_prep(int T, int B, int H, int cell, float *zin, const float *zh,
+                            const float *c0, float *cs, cudaStream_t s) {
+  const int n = B * H;
+  bwd_prep_kernel<<<ceil_div(n, 256), 256, 0, s>>>(T, B, H, cell, zin, zh, c0, cs);
+  return cudaGetLastError();
+}
+
+int bwd_units_per_cta(int H, int B, int nG, int nsm) {
+  // as many CTAs as there are SMs (the launch is cooperative: all resident)
+  const int U = std::max(1, ceil_div(H, nsm));
+  return rec_smem(U, nG * H, B) <= (size_t)227 * 1024 ? U : 0;
+}
+
+cudaError_t launch_bwd_rec(const BwdRecArgs &a, int nsm, cudaStream_t s) {
+  const int nG = a.cell == CELL_LSTM ? 4 : 3;
+  const int U = bwd_units_per_cta(a.H, a.B, nG, nsm);
+  if (U < 1) return cudaErrorInvalidConfiguration;
+  BwdParams p{};
+  p.T = a.T; p.B = a.B; p.H = a.H; p.cell = a.cell; p.U = U;
+  p.Whh = a.Whh; p.ldw = a.ldw;
+  p.gates = a.gates; p.zh = a.zh; p.cs = a.cs; p.c0 = a.c0; p.hp = a.hp;
+  p.dy = a.dy; p.dhn = a.dhn; p.dcn = a.dcn;
+  p.DA = a.DA; p.DR = a.DR; p.dh0 = a.dh0; p.dc0 = a.dc0;
+  p.ctr = a.ctr; p.err = a.err; p.timeout_ns = a.timeout_ns;
+  const size_t smem = rec_smem(U, nG * a.H, a.B);
+  cudaError_t e = cudaFuncSetAttribute((const void *)bwd_rec_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  void *args[] = {&p};
+  return cudaLaunchCooperativeKernel((const void *)bwd_rec_kernel, dim3(ceil_div(a.H, U)),
+                                     dim3(NT), args, smem, s);
+}
+
+cudaError_t launch_transpose(const float *in, int R, int C, int ldi, float *out, int ldo,
+                             cudaStream_t s) {
+  if (R <= 0 || C <= 0) return cudaSuccess;
+  transpose_kernel<<<dim3(ceil_div(C, 32), ceil_div(R, 32)), dim3(32, 8), 0, s>>>(in, R, C, ldi,
+                                                                                    out, ldo);
+  return cudaGetLastError();
+}
+
+size_t colsum_scratch_floats(int M, int N) { return (size_t)ceil_div(M, CS_ROWS) * N; }
+
+cudaError_t launch_colsum(const float *A, int M, int N, float *scratch, float *out,
+                          cudaStream_t s) {
+  const int chunks = ceil_div(M, CS_ROWS);
+  colsum_partial_kernel<<<dim3(ceil_div(N, 256), chunks), 256, 0, s>>>(A, M, N, scratch);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  colsum_final_kernel<<<ceil_div(N, 256), 256, 0, s>>>(scratch, chunks, N, out);
+  return cudaGetLastError();
+}
+
+}  // namespace rcu

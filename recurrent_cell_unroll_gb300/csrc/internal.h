@@ -123,4 +123,28 @@ cudaError_t launch_rssm(const RssmParams &p, int nsm, cudaStream_t s, int *clust
 // the weights (and, with Hx > 0, the actor's) fit one cluster's shared memory
 bool rssm_supported(int S, int A, int Hd, int RH, int Hx = 0);
 
+// ---- backward.cu: backward pass through time (fp32, unidirectional) ---------
+// zin: X W_ih^T + b_ih in, activated gates out; zh: H_prev W_hh^T + b_hh;
+// cs: LSTM cell sequence out.  Parallel over B*H, sequential over T.
+cudaError_t launch_bwd_prep(int T, int B, int H, int cell, float *zin, const float *zh,
+                            const float *c0, float *cs, cudaStream_t s);
+struct BwdRecArgs {
+  int T, B, H, cell;
+  const float *Whh;  // [nG*H][ldw]
+  int ldw;
+  const float *gates, *zh, *cs, *c0, *hp, *dy, *dhn, *dcn;
+  float *DA, *DR, *dh0, *dc0;
+  unsigned *ctr;  // zeroed before the launch
+  int *err;
+  uint64_t timeout_ns;
+};
+// hidden units per CTA of the reverse-time kernel, 0 if W_hh^T does not fit
+int bwd_units_per_cta(int H, int B, int nG, int nsm);
+cudaError_t launch_bwd_rec(const BwdRecArgs &a, int nsm, cudaStream_t s);
+cudaError_t launch_transpose(const float *in, int R, int C, int ldi, float *out, int ldo,
+                             cudaStream_t s);
+size_t colsum_scratch_floats(int M, int N);
+cudaError_t launch_colsum(const float *A, int M, int N, float *scratch, float *out,
+                          cudaStream_t s);
+
 }  // namespace rcu

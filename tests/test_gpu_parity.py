@@ -674,3 +674,73 @@ def test_full_size_sampled_rows(spec, rows):
         L = inp["lengths"].numpy()
         for b in range(spec.B):
             assert np.all(got[0][L[b]:, b] == 0.0)
+
+
+# ----------------------------------------------------------------------------- backward (BPTT)
+
+BWD_REL = 1e-4  # per tensor: max|gpu - ref| / max|ref| (fp32 sums over T*B terms, T steps)
+
+BWD_SPECS = [
+    wl.LSTM_T80.scaled(T=7, B=5, in_dim=12, hidden=20, layers=2, h0_std=0.5, c0_std=0.5),
+    wl.GRU_3L.scaled(T=6, B=9, in_dim=16, hidden=24, layers=2, dtype="f32"),
+    wl.GRU_3L.scaled(T=5, B=3, in_dim=7, hidden=13, layers=1, dtype="f32", h0_std=0.3),
+    wl.LSTM_T80.scaled(T=32, B=64, in_dim=256, hidden=512, layers=1),
+    wl.GRU_3L.scaled(T=24, B=32, in_dim=128, hidden=256, layers=3, dtype="f32", h0_std=0.1),
+]
+
+
+def _rel(a, b):
+    return float(np.abs(a - b).max() / max(np.abs(b).max(), 1e-30))
+
+
+@pytest.mark.parametrize("spec", BWD_SPECS, ids=lambda s: f"{s.cell}-L{s.layers}-T{s.T}-B{s.B}-H{s.hidden}")
+def test_backward_parity(spec):
+    inp = wl.make_rnn_inputs(spec, seed=12)
+    g = torch.Generator().manual_seed(99)
+    L, B, H = spec.layers, spec.B, spec.hidden
+    dy = torch.randn((spec.T, B, H), generator=g)
+    dhn = torch.randn((L, B, H), generator=g)
+    dcn = torch.randn((L, B, H), generator=g) if spec.cell == "lstm" else None
+    dev = torch.device("cuda")
+    net = binding.RNN.from_spec(spec)
+    net.set_weights(inp["weights"])
+
+    def d(t):
+        return None if t is None else t.to(dev)
+    dx, dh0, dc0, grads = net.backward(d(inp["x"]), d(dy), h0=d(inp["h0"]), c0=d(inp["c0"]),
+                                       dh_n=d(dhn), dc_n=d(dcn))
+    torch.cuda.synchronize()
+    assert net.status() == 0
+    ref = oracle.rnn_backward(_cell(spec), inp["x"], inp["weights"], dy, hidden=H, h0=inp["h0"],
+                              c0=inp["c0"], dh_n=dhn, dc_n=dcn)
+    pairs = [("dx", dx, ref["dx"]), ("dh0", dh0, ref["dh0"])]
+    if spec.cell == "lstm":
+        pairs.append(("dc0", dc0, ref["dc0"]))
+    for layer in range(L):
+        for k in ("w_ih", "w_hh", "b_ih", "b_hh"):
+            pairs.append((f"d{k}[{layer}]", grads[layer][k], ref["d" + k][layer]))
+    for name, got, want in pairs:
+        e = _rel(got.cpu().numpy().astype(np.float64), want)
+        print(f"{name}: rel {e:.2e}")
+        assert e <= BWD_REL, f"{name}: relative max error {e:.3e}"
+    net.close()
+
+
+def test_backward_errors():
+    spec = BWD_SPECS[0]
+    inp = wl.make_rnn_inputs(spec, seed=1)
+    dev = torch.device("cuda")
+    net = binding.RNN.from_spec(spec)
+    net.set_weights(inp["weights"])
+    with pytest.raises(RuntimeError, match="no rnn_backward"):
+        binding.rnn_get_weight_grads(net.h, 0, None, None, None, None)
+    net.close()
+    for bad in (spec.scaled(dtype="bf16"), spec.scaled(bidir=True), spec.scaled(proj=8)):
+        net = binding.RNN.from_spec(bad)
+        net.set_weights(wl.make_rnn_inputs(bad, seed=1)["weights"])
+        x = torch.zeros((bad.T, bad.B, bad.in_dim), device=dev)
+        dy = torch.zeros((bad.T, bad.B, bad.D * bad.Hout), device=dev)
+        with pytest.raises(RuntimeError, match="fp32 unidirectional"):
+            binding.rnn_backward(net.h, bad.T, bad.B, x, None, None, dy, None, None, None, None,
+                                 None)
+        net.close()
