@@ -36,6 +36,7 @@ from recurrent_cell_unroll_gb300 import workloads as wl  # noqa: E402
 WORKLOADS = {
     "lstm": wl.LSTM_T80, "rssm": wl.RSSM_B50, "lstmp": wl.LSTMP_2L,
     "bilstm": wl.BILSTM_VAR, "gru": wl.GRU_3L, "rssm_actor": wl.RSSM_ACTOR,
+    "lstm_train": wl.LSTM_TRAIN,
 }
 METRIC = "(batch×timesteps)/s"
 UNIT = "(B·T)/s"
@@ -109,7 +110,17 @@ def kernel_flops(spec, inp) -> dict:
         K = spec.in_dim if layer == 0 else D * Ho
         gemm.append(2 * M * D * nG * H * K)
         rec.append(2 * M * D * (nG * H * Ho + (P * H if P else 0)))
-    return {"input_gemm": gemm, "recurrent": rec}
+    out = {"input_gemm": gemm, "recurrent": rec}
+    if getattr(spec, "train", False):
+        # backward through time: dh recurrence W_hh^T dz, dW_ih, dW_hh, dX; the
+        # recompute GEMMs repeat the forward's (counted, they run)
+        G = nG * H
+        ks = [spec.in_dim if layer == 0 else H for layer in range(spec.layers)]
+        out["bwd_recompute_gemm"] = [2 * M * G * (k + H) for k in ks]
+        out["bwd_recurrent"] = [2 * M * G * H for _ in ks]
+        out["bwd_weight_gemm"] = [2 * M * G * (k + H) for k in ks]
+        out["bwd_dx_gemm"] = [2 * M * G * k for k in ks]
+    return out
 
 
 def total_flops(spec, inp) -> int:
@@ -249,6 +260,8 @@ def make_runner(spec, inp, dev, tc_ksplit=0):
     net.set_weights(inp["weights"], device=dev)
     d = {k: (None if inp[k] is None else inp[k].to(dev)) for k in ("x", "lengths", "h0", "c0")}
     T, B = spec.T, spec.B
+    if spec.train:
+        return make_train_runner(spec, inp, dev, net, d)
     y = torch.empty((T, B, spec.D * spec.Hout), device=dev)
     hn = torch.empty((spec.layers * spec.D, B, spec.Hout), device=dev)
     cn = torch.empty((spec.layers * spec.D, B, spec.hidden), device=dev) \
@@ -286,6 +299,59 @@ def make_runner(spec, inp, dev, tc_ksplit=0):
     return step, launches, profile_on, profile_read, e2e_io, status, net
 
 
+def make_train_runner(spec, inp, dev, net, d):
+    """A training pass: rnn_backward (which runs the forward again keeping every
+    layer's output) and the weight gradients of every layer."""
+    from recurrent_cell_unroll_gb300 import binding
+    T, B, H, L = spec.T, spec.B, spec.hidden, spec.layers
+    nG = spec.nG
+    dy = inp["dy"].to(dev)
+    dx = torch.empty_like(d["x"])
+    dh0 = torch.empty((L, B, H), device=dev)
+    dc0 = torch.empty_like(dh0) if spec.cell == "lstm" else None
+    grads = []
+    for layer in range(L):
+        k = spec.in_dim if layer == 0 else H
+        grads.append([torch.empty((nG * H, k), device=dev), torch.empty((nG * H, H), device=dev),
+                      torch.empty((nG * H,), device=dev), torch.empty((nG * H,), device=dev)])
+
+    def step():
+        binding.rnn_backward(net.h, T, B, d["x"], d["h0"], d["c0"], dy, None, None, dx, dh0, dc0)
+        for layer in range(L):
+            binding.rnn_get_weight_grads(net.h, layer, *grads[layer])
+
+    def launches():
+        return net.launch_count()
+
+    def profile_on():
+        net.set_attr(binding.RCU_ATTR_PROFILE, 1)
+        binding.rnn_profile_reset(net.h)
+
+    def profile_read():
+        prof = net.profile()
+        net.set_attr(binding.RCU_ATTR_PROFILE, 0)
+        return prof
+
+    def e2e_io():
+        # no host-buffer form of the backward: pinned host tensors copied in and
+        # out around the device call, all on the launching stream
+        hin = {"x": inp["x"].contiguous().pin_memory(), "dy": inp["dy"].contiguous().pin_memory()}
+        outs = [dx] + [g for gl in grads for g in gl]
+        hout = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+
+        def call():
+            d["x"].copy_(hin["x"], non_blocking=True)
+            dy.copy_(hin["dy"], non_blocking=True)
+            step()
+            for o, hbuf in zip(outs, hout):
+                hbuf.copy_(o, non_blocking=True)
+        return list(hin.values()), hout, call
+
+    def status():
+        return net.status()
+    return step, launches, profile_on, profile_read, e2e_io, status, net
+
+
 def roofline(spec, inp, prof, peaks, nsm, step_ms=None):
     """Roofline of the dominant kernel from the live event timings."""
     if isinstance(spec, wl.RssmSpec):
@@ -302,7 +368,7 @@ def roofline(spec, inp, prof, peaks, nsm, step_ms=None):
         return None
     name, (ms, n) = max(prof.items(), key=lambda kv: kv[1][0])
     fl = kernel_flops(spec, inp)
-    kind = "recurrent" if name.startswith("recurrent") else (
+    kind = name if name in fl else "recurrent" if name.startswith("recurrent") else (
         "input_gemm" if name.startswith("input_gemm") else None)
     if kind is None:
         return None
@@ -402,7 +468,9 @@ def run_ours(args, spec, rank, local, ws):
                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                "call": ("rssm_unroll_actor_host" if getattr(spec, "actor_hidden", 0) else
                         "rssm_unroll_host") if isinstance(spec, wl.RssmSpec) else
-               "rnn_forward_host", "host_buffers": "pinned"}
+               ("rnn_backward + rnn_get_weight_grads, pinned host copies on the stream"
+                if getattr(spec, "train", False) else "rnn_forward_host"),
+               "host_buffers": "pinned"}
 
     peaks = load_peaks()
     extra = {}
@@ -464,6 +532,9 @@ def compulsory_bytes(spec, inp) -> int:
     M = active_rows(spec, inp)
     x = M * spec.in_dim * 4
     y = spec.T * spec.B * D * Ho * 4
+    if getattr(spec, "train", False):
+        # x and dy in, dx and the weight gradients out
+        return 2 * w + 2 * x + y
     st = spec.layers * D * spec.B * (Ho + (H if spec.cell == "lstm" else 0)) * 4
     h0 = st if (inp.get("h0") is not None) else 0
     return w + x + y + st + h0
@@ -478,7 +549,7 @@ def workload_config(spec, inp, ws):
                  rnn_hidden=spec.rnn_hidden, actor_hidden=spec.actor_hidden or None)
     else:
         c.update(cell=spec.cell, layers=spec.layers, in_dim=spec.in_dim, hidden=spec.hidden,
-                 proj=spec.proj, bidirectional=spec.bidir,
+                 proj=spec.proj, bidirectional=spec.bidir, train=spec.train or None,
                  varlen=None if inp.get("lengths") is None else
                  {"sum_len": int(inp["lengths"].sum()), "range": list(spec.varlen)})
     c["l2_flush_each_step"] = True
@@ -503,6 +574,13 @@ def oracle_sample(spec, inp, rows, threads):
     elif isinstance(spec, wl.RssmSpec):
         oracle.rssm_unroll(inp["weights"], inp["actions"], inp["eps"], state0=inp["state0"],
                            belief0=inp["belief0"], rows=rows, threads=threads)
+    elif spec.train:
+        sel = list(rows)
+        sub = (lambda t, dim: None if t is None else t[:, sel] if dim == 1 else t[sel])
+        oracle.rnn_backward(oracle.LSTM if spec.cell == "lstm" else oracle.GRU,
+                            sub(inp["x"], 1), inp["weights"], sub(inp["dy"], 1),
+                            hidden=spec.hidden, h0=sub(inp["h0"], 1), c0=sub(inp["c0"], 1),
+                            threads=threads)
     else:
         oracle.rnn_forward(oracle.LSTM if spec.cell == "lstm" else oracle.GRU, inp["x"],
                            inp["weights"], hidden=spec.hidden, proj=spec.proj,

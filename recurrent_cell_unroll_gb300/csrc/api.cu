@@ -1009,7 +1009,9 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
   const size_t o_keep = take((size_t)L * TBH), o_hp = take(TBH), o_zin = take(TBG),
                o_zh = take(TBG), o_cs = take(cell == RCU_LSTM ? TBH : 0), o_da = take(TBG),
                o_dr = take(cell == RCU_GRU ? TBG : 0), o_dya = take(TBH), o_dyb = take(TBH),
-               o_t1 = take(TBG), o_t2 = take((size_t)M * kmax), o_wt = take((size_t)kmax * G),
+               o_t1 = take(TBG), o_t2 = take((size_t)M * kmax),
+               o_t3 = take(cell == RCU_GRU ? TBG : 0), o_t4 = take(TBH),
+               o_wt = take((size_t)kmax * G),
                o_cs2 = take(colsum_scratch_floats(M, G)), o_ctl = take(64);
   CU(h->bw.ensure(off * 4));
   float *wsf = (float *)h->bw.p;
@@ -1017,6 +1019,7 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
   float *cs = cell == RCU_LSTM ? wsf + o_cs : nullptr, *DA = wsf + o_da;
   float *DR = cell == RCU_GRU ? wsf + o_dr : DA;
   float *dYa = wsf + o_dya, *dYb = wsf + o_dyb, *T1 = wsf + o_t1, *T2 = wsf + o_t2;
+  float *T3 = cell == RCU_GRU ? wsf + o_t3 : T1, *T4 = wsf + o_t4;
   float *WT = wsf + o_wt, *csum = wsf + o_cs2;
   unsigned *ctr = (unsigned *)(wsf + o_ctl);
   if ((int)h->gw.size() < L) h->gw.resize(L);
@@ -1044,6 +1047,7 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
       CU(cudaMemcpyAsync(hp + (size_t)B * H, keep + (size_t)l * TBH, (size_t)(T - 1) * B * H * 4,
                          cudaMemcpyDeviceToDevice, s));
     // pre-activations of every step
+    h->begin("bwd_recompute_gemm", s);
     cudaError_t e = launch_gemm_simt<float, float>(X, K, (const float *)h->wih[l].p, ldk,
                                                    (const float *)lw.bih_plain.p, zin, G, M,
                                                    nullptr, G, K, s, err);
@@ -1051,8 +1055,11 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
       e = launch_gemm_simt<float, float>(hp, H, (const float *)lw.whh_plain.p, ldh,
                                          (const float *)lw.bhh_plain.p, zh, G, M, nullptr, G, H,
                                          s, err);
+    h->end(s);
     const float *c0l = c0 ? c0 + (size_t)l * B * H : nullptr;
+    h->begin("bwd_prep", s);
     if (e == cudaSuccess) e = launch_bwd_prep(T, B, H, cell, zin, zh, c0l, cs, s);
+    h->end(s);
     if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: recompute: %s", cudaGetErrorString(e));
     // the reverse-time recurrence
     CU(cudaMemsetAsync(ctr, 0, 16 * 4, s));
@@ -1066,29 +1073,40 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
     a.dh0 = dh0 ? dh0 + (size_t)l * B * H : nullptr;
     a.dc0 = dc0 ? dc0 + (size_t)l * B * H : nullptr;
     a.ctr = ctr; a.err = err; a.timeout_ns = (uint64_t)h->timeout_ns;
+    h->begin("bwd_recurrent", s);
     e = launch_bwd_rec(a, h->nsm, s);
+    h->end(s);
     if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: recurrence: %s", cudaGetErrorString(e));
-    // weight gradients: dW_ih = DA^T X, dW_hh = DR^T H_prev, db = column sums
+    // weight gradients: dW_ih = DA^T X, dW_hh = DR^T H_prev (through transposes
+    // to K-contiguous operands), db = column sums; input gradient dX = DA W_ih
     DevBuf &g = h->gw[l];
     CU(g.ensure(((size_t)G * K + (size_t)G * H + 2 * (size_t)G) * 4));
     float *gWih = (float *)g.p, *gWhh = gWih + (size_t)G * K, *gbih = gWhh + (size_t)G * H,
           *gbhh = gbih + G;
+    h->begin("bwd_transpose", s);
     e = launch_transpose(DA, M, G, G, T1, M, s);
     if (e == cudaSuccess) e = launch_transpose(X, M, K, K, T2, M, s);
+    if (e == cudaSuccess && cell == RCU_GRU) e = launch_transpose(DR, M, G, G, T3, M, s);
+    if (e == cudaSuccess) e = launch_transpose(hp, M, H, H, T4, M, s);
+    if (e == cudaSuccess) e = launch_transpose((const float *)h->wih[l].p, G, K, ldk, WT, G, s);
+    h->end(s);
+    h->begin("bwd_weight_gemm", s);
     if (e == cudaSuccess)
       e = launch_gemm_simt<float, float>(T1, M, T2, M, nullptr, gWih, K, G, nullptr, K, M, s, err);
-    if (e == cudaSuccess) e = launch_transpose(DR, M, G, G, T1, M, s);
-    if (e == cudaSuccess) e = launch_transpose(hp, M, H, H, T2, M, s);
     if (e == cudaSuccess)
-      e = launch_gemm_simt<float, float>(T1, M, T2, M, nullptr, gWhh, H, G, nullptr, H, M, s, err);
+      e = launch_gemm_simt<float, float>(T3, M, T4, M, nullptr, gWhh, H, G, nullptr, H, M, s, err);
+    h->end(s);
+    h->begin("bwd_colsum", s);
     if (e == cudaSuccess) e = launch_colsum(DA, M, G, csum, gbih, s);
     if (e == cudaSuccess) e = launch_colsum(DR, M, G, csum, gbhh, s);
-    // input gradient dX = DA W_ih (W_ih transposed to [K][G])
-    if (e == cudaSuccess) e = launch_transpose((const float *)h->wih[l].p, G, K, ldk, WT, G, s);
+    h->end(s);
+    h->begin("bwd_dx_gemm", s);
     if (e == cudaSuccess && dX)
       e = launch_gemm_simt<float, float>(DA, G, WT, G, nullptr, dX, K, M, nullptr, K, G, s, err);
+    h->end(s);
     if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: gradients: %s", cudaGetErrorString(e));
-    launches += 16;  // 5 GEMMs, 5 transposes, prep, recurrence, 2 two-kernel column sums
+    // 5 GEMMs, 4 or 5 transposes, prep, recurrence, 2 two-kernel column sums
+    launches += cell == RCU_GRU ? 16 : 15;
     dYcur = dX;
     if (l > 0 && !dX) return fail(RCU_ERR_INVALID, "rnn_backward: internal");
   }

@@ -60,8 +60,22 @@ __global__ void bwd_prep_kernel(int T, int B, int H, int cell, float *__restrict
   }
 }
 
+constexpr int UMAX = 8;  // hidden units per CTA (register tile width)
+
+// 16-byte asynchronous global -> shared copy (cached in L2 only)
+__device__ __forceinline__ void cp_async16(float *dst, const float *src) {
+  const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 struct BwdParams {
   int T, B, H, cell, U;
+  int Gp, KC, KS;     // gate width padded to 4; staged chunk of dR columns; K slices
   const float *Whh;   // [nG*H][ldw], PyTorch row order
   int ldw;
   const float *gates; // [T*B][G] activated gates
@@ -84,14 +98,17 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
   const bool lstm = p.cell == CELL_LSTM;
   const int G = (lstm ? 4 : 3) * H;
   const int u0 = blockIdx.x * U, nu = max(0, min(U, H - u0));
-  float *WT = sm;                        // [U][G]: WT[j][n] = W_hh[n][u0 + j]
-  float *dhrec = WT + (size_t)U * G;     // [B][U]: W_hh^T dR part of dh_t (+ direct GRU path)
+  const int Gp = p.Gp, KC = p.KC, KS = p.KS, KCP = KC + 4;
+  float *WT = sm;                        // [U][Gp]: WT[j][n] = W_hh[n][u0 + j], zero padded
+  float *xs = WT + (size_t)U * Gp;       // [2][B][KCP]: staged columns of dR_t (double buffer)
+  float *part = xs + 2 * (size_t)B * KCP;  // [KS][B][U]: K-slice partial sums
+  float *dhrec = part + (size_t)KS * B * U;  // [B][U]: W_hh^T dR part of dh_t (+ direct GRU path)
   float *dcs = dhrec + (size_t)B * U;    // [B][U]: LSTM dc carried to the previous step
   float *dhz = dcs + (size_t)B * U;      // [B][U]: GRU z * dh (direct path)
   const int tid = threadIdx.x;
-  for (int e = tid; e < U * G; e += NT) {
-    const int j = e / G, n = e % G;
-    WT[e] = j < nu ? p.Whh[(size_t)n * p.ldw + u0 + j] : 0.f;
+  for (int e = tid; e < U * Gp; e += NT) {
+    const int j = e / Gp, n = e % Gp;
+    WT[e] = (j < nu && n < G) ? p.Whh[(size_t)n * p.ldw + u0 + j] : 0.f;
   }
   for (int e = tid; e < B * U; e += NT) {
     const int b = e / U, j = e % U;
@@ -102,6 +119,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
   }
   __syncthreads();
   const bool vec = (G & 3) == 0;
+  const int RG = ceil_div(B, 4);
   for (int t = p.T - 1, it = 1; t >= 0; --t, ++it) {
     // ---- gate gradients of this CTA's units at step t
     for (int e = tid; e < B * U; e += NT) {
@@ -140,27 +158,90 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
     }
     // every CTA's gate gradients of step t are published
     if (!group_barrier(p.ctr, (unsigned)it * gridDim.x, p.err, p.timeout_ns)) return;
-    // ---- dh_{t-1} of this CTA's units: W_hh^T dR_t (+ z dh)
+    // ---- dh_{t-1} of this CTA's units: W_hh^T dR_t (+ z dh).  dR_t is staged
+    // in chunks of KC columns with coalesced loads; thread (row group of 4,
+    // K slice) keeps a 4 x U register tile and walks the chunk's float4
+    // columns interleaved by K slice (consecutive threads read consecutive
+    // 16-byte words: no bank conflicts); the K-slice partials are summed last.
     const float *drt = (lstm ? p.DA : p.DR) + (size_t)t * B * G;
-    for (int e = tid; e < B * U; e += NT) {
-      const int b = e / U, j = e % U;
-      if (j >= nu) continue;
-      const float *v = drt + (size_t)b * G, *w = WT + (size_t)j * G;
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-      int n = 0;
-      if (vec) {
-#pragma unroll 4
-        for (; n + 3 < G; n += 4) {
-          const float4 x = __ldcg(reinterpret_cast<const float4 *>(v + n));
-          const float4 y = *reinterpret_cast<const float4 *>(w + n);
-          a0 = fmaf(x.x, y.x, a0);
-          a1 = fmaf(x.y, y.y, a1);
-          a2 = fmaf(x.z, y.z, a2);
-          a3 = fmaf(x.w, y.w, a3);
+    const int rg = tid / KS, ksl = tid % KS;
+    const bool comp = rg < RG;
+    float acc[4][UMAX];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int j = 0; j < UMAX; ++j) acc[r][j] = 0.f;
+    const int nch = ceil_div(Gp, KC);
+    // stage chunk c of dR_t into buffer c & 1: cp.async when rows are 16-byte
+    // aligned (G a multiple of 4), else plain loads
+    auto stage = [&](int c) {
+      const int k0 = c * KC, kc4 = min(KC, Gp - k0) >> 2;
+      float *xb = xs + (size_t)(c & 1) * B * KCP;
+      for (int e = tid; e < B * kc4; e += NT) {
+        const int b = e / kc4, q = e % kc4, k = k0 + 4 * q;
+        const float *src = drt + (size_t)b * G + k;
+        float *dst = xb + (size_t)b * KCP + 4 * q;
+        if (vec) {
+          cp_async16(dst, src);
+        } else {
+          float4 v;
+          v.x = k < G ? __ldcg(src) : 0.f;
+          v.y = k + 1 < G ? __ldcg(src + 1) : 0.f;
+          v.z = k + 2 < G ? __ldcg(src + 2) : 0.f;
+          v.w = k + 3 < G ? __ldcg(src + 3) : 0.f;
+          *reinterpret_cast<float4 *>(dst) = v;
         }
       }
-      for (; n < G; ++n) a0 = fmaf(__ldcg(v + n), w[n], a0);
-      dhrec[e] = (lstm ? 0.f : dhz[e]) + ((a0 + a1) + (a2 + a3));
+      cp_async_commit();
+    };
+    stage(0);
+    for (int c = 0; c < nch; ++c) {
+      if (c + 1 < nch) {
+        stage(c + 1);
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
+      }
+      __syncthreads();
+      const int k0 = c * KC, kc4 = min(KC, Gp - k0) >> 2;
+      const float *xb = xs + (size_t)(c & 1) * B * KCP;
+      if (comp) {
+        for (int q = ksl; q < kc4; q += KS) {
+          float4 x[4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int b = 4 * rg + r;
+            x[r] = b < B ? *reinterpret_cast<const float4 *>(xb + (size_t)b * KCP + 4 * q)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int j = 0; j < UMAX; ++j) {
+            if (j >= U) break;
+            const float4 w = *reinterpret_cast<const float4 *>(WT + (size_t)j * Gp + k0 + 4 * q);
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+              acc[r][j] = fmaf(x[r].x, w.x, fmaf(x[r].y, w.y, fmaf(x[r].z, w.z,
+                                                   fmaf(x[r].w, w.w, acc[r][j]))));
+          }
+        }
+      }
+      __syncthreads();  // buffer c & 1 is refilled by stage(c + 2)
+    }
+    if (comp) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int b = 4 * rg + r;
+        if (b >= B) break;
+#pragma unroll
+        for (int j = 0; j < UMAX; ++j)
+          if (j < U) part[((size_t)ksl * B + b) * U + j] = acc[r][j];
+      }
+    }
+    __syncthreads();
+    for (int e = tid; e < B * U; e += NT) {
+      float v = 0.f;
+      for (int q = 0; q < KS; ++q) v += part[(size_t)q * B * U + e];
+      dhrec[e] = (lstm ? 0.f : dhz[e]) + v;
     }
     __syncthreads();
   }
@@ -209,7 +290,28 @@ __global__ void colsum_final_kernel(const float *__restrict__ part, int chunks, 
   out[n] = s;
 }
 
-size_t rec_smem(int U, int G, int B) { return ((size_t)U * G + 3 * (size_t)B * U) * sizeof(float); }
+struct RecPlan { int U, Gp, KC, KS; size_t smem; };
+size_t rec_smem(int U, int Gp, int B, int KC, int KS) {
+  return ((size_t)U * Gp + 2 * (size_t)B * (KC + 4) + (size_t)KS * B * U + 3 * (size_t)B * U) *
+         sizeof(float);
+}
+// U = units per CTA (one CTA per SM at most), K slices so that (row groups of
+// 4) x slices fill the CTA, chunk width KC (a multiple of 4 * KS) as large as
+// shared memory allows, at most 512 columns
+RecPlan plan_rec(int H, int B, int nG, int nsm) {
+  RecPlan r{};
+  r.U = std::max(1, ceil_div(H, nsm));
+  r.Gp = round_up(nG * H, 4);
+  const int RG = ceil_div(B, 4);
+  r.KS = std::max(1, std::min(32, NT / RG));
+  if (r.U > UMAX || RG > NT) return RecPlan{};
+  r.KC = std::min(512, round_up(r.Gp, 4 * r.KS));
+  while (r.KC > 4 * r.KS && rec_smem(r.U, r.Gp, B, r.KC, r.KS) > (size_t)227 * 1024)
+    r.KC -= 4 * r.KS;
+  r.smem = rec_smem(r.U, r.Gp, B, r.KC, r.KS);
+  if (r.smem > (size_t)227 * 1024) return RecPlan{};
+  return r;
+}
 
 }  // namespace
 
@@ -220,24 +322,22 @@ cudaError_t launch_bwd_prep(int T, int B, int H, int cell, float *zin, const flo
   return cudaGetLastError();
 }
 
-int bwd_units_per_cta(int H, int B, int nG, int nsm) {
-  // as many CTAs as there are SMs (the launch is cooperative: all resident)
-  const int U = std::max(1, ceil_div(H, nsm));
-  return rec_smem(U, nG * H, B) <= (size_t)227 * 1024 ? U : 0;
-}
+int bwd_units_per_cta(int H, int B, int nG, int nsm) { return plan_rec(H, B, nG, nsm).U; }
 
 cudaError_t launch_bwd_rec(const BwdRecArgs &a, int nsm, cudaStream_t s) {
   const int nG = a.cell == CELL_LSTM ? 4 : 3;
-  const int U = bwd_units_per_cta(a.H, a.B, nG, nsm);
-  if (U < 1) return cudaErrorInvalidConfiguration;
+  const RecPlan rp = plan_rec(a.H, a.B, nG, nsm);
+  if (rp.U < 1) return cudaErrorInvalidConfiguration;
+  const int U = rp.U;
   BwdParams p{};
   p.T = a.T; p.B = a.B; p.H = a.H; p.cell = a.cell; p.U = U;
+  p.Gp = rp.Gp; p.KC = rp.KC; p.KS = rp.KS;
   p.Whh = a.Whh; p.ldw = a.ldw;
   p.gates = a.gates; p.zh = a.zh; p.cs = a.cs; p.c0 = a.c0; p.hp = a.hp;
   p.dy = a.dy; p.dhn = a.dhn; p.dcn = a.dcn;
   p.DA = a.DA; p.DR = a.DR; p.dh0 = a.dh0; p.dc0 = a.dc0;
   p.ctr = a.ctr; p.err = a.err; p.timeout_ns = a.timeout_ns;
-  const size_t smem = rec_smem(U, nG * a.H, a.B);
+  const size_t smem = rp.smem;
   cudaError_t e = cudaFuncSetAttribute((const void *)bwd_rec_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

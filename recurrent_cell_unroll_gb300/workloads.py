@@ -40,6 +40,7 @@ class RnnSpec:
     varlen: Optional[tuple] = None   # (min_len, max_len) inclusive, or None
     h0_std: float = 0.0    # > 0: h0 ~ N(0, h0_std^2); 0: h0 = c0 = zero (NULL)
     c0_std: float = 0.0
+    train: bool = False    # a training pass: forward + backward through time given dy
 
     @property
     def D(self) -> int:
@@ -84,9 +85,13 @@ BILSTM_VAR = RnnSpec("bilstm_f32_varlen_B64_T500_256x512", "lstm", 1, 256, 512, 
                      bidir=True, varlen=(50, 500))
 GRU_3L = RnnSpec("gru_bf16_3L_T512_B256_1024", "gru", 3, 1024, 1024, T=512, B=256, dtype="bf16",
                  h0_std=0.1)
+# forward + backward through time of the unidirectional form of the varlen
+# shape (256 -> 512, B = 64, T = 500); dy ~ N(0, 1)
+LSTM_TRAIN = RnnSpec("lstm_train_f32_T500_B64_256x512", "lstm", 1, 256, 512, T=500, B=64,
+                     train=True)
 
 WORKLOADS = {s.name: s for s in (LSTM_T80, RSSM_B50, LSTMP_2L, BILSTM_VAR, GRU_3L,
-                                  RSSM_ACTOR)}
+                                  RSSM_ACTOR, LSTM_TRAIN)}
 
 
 def _uniform(g, shape, bound):
@@ -121,7 +126,10 @@ def make_rnn_inputs(spec: RnnSpec, seed: int = 0, bias: bool = True) -> dict:
         h0 = torch.randn((LD, spec.B, Hout), generator=g, dtype=torch.float32) * spec.h0_std
     if spec.c0_std > 0 and spec.cell == "lstm":
         c0 = torch.randn((LD, spec.B, H), generator=g, dtype=torch.float32) * spec.c0_std
-    return {"weights": weights, "x": x, "lengths": lengths, "h0": h0, "c0": c0}
+    out = {"weights": weights, "x": x, "lengths": lengths, "h0": h0, "c0": c0}
+    if spec.train:  # drawn last: the other draws stay those of the forward workload
+        out["dy"] = torch.randn((spec.T, spec.B, D * Hout), generator=g, dtype=torch.float32)
+    return out
 
 
 def make_rssm_inputs(spec: RssmSpec, seed: int = 0) -> dict:
