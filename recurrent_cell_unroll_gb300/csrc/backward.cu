@@ -60,7 +60,7 @@ __global__ void bwd_prep_kernel(int T, int B, int H, int cell, float *__restrict
   }
 }
 
-constexpr int UMAX = 8;  // hidden units per CTA (register tile width)
+constexpr int UMAX = 16;  // hidden units per CTA (register tile width)
 
 // 16-byte asynchronous global -> shared copy (cached in L2 only)
 __device__ __forceinline__ void cp_async16(float *dst, const float *src) {
@@ -76,6 +76,7 @@ __device__ __forceinline__ void cp_async_wait() {
 struct BwdParams {
   int T, B, H, cell, U;
   int Gp, KC, KS;     // gate width padded to 4; staged chunk of dR columns; K slices
+  int BS, NUG;        // batch rows per CTA; unit groups (CTA = batch group x unit group)
   const float *Whh;   // [nG*H][ldw], PyTorch row order
   int ldw;
   const float *gates; // [T*B][G] activated gates
@@ -97,35 +98,40 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
   const int H = p.H, B = p.B, U = p.U;
   const bool lstm = p.cell == CELL_LSTM;
   const int G = (lstm ? 4 : 3) * H;
-  const int u0 = blockIdx.x * U, nu = max(0, min(U, H - u0));
+  // CTA = (batch group bgi: rows [b0, b0 + Bl), unit group ug: units [u0, u0 + nu));
+  // batch groups never wait on each other (rows are independent)
+  const int BS = p.BS, ug = blockIdx.x % p.NUG, bgi = blockIdx.x / p.NUG;
+  const int b0 = bgi * BS, Bl = max(0, min(BS, B - b0));
+  const int u0 = ug * U, nu = max(0, min(U, H - u0));
   const int Gp = p.Gp, KC = p.KC, KS = p.KS, KCP = KC + 4;
   float *WT = sm;                        // [U][Gp]: WT[j][n] = W_hh[n][u0 + j], zero padded
-  float *xs = WT + (size_t)U * Gp;       // [2][B][KCP]: staged columns of dR_t (double buffer)
-  float *part = xs + 2 * (size_t)B * KCP;  // [KS][B][U]: K-slice partial sums
-  float *dhrec = part + (size_t)KS * B * U;  // [B][U]: W_hh^T dR part of dh_t (+ direct GRU path)
-  float *dcs = dhrec + (size_t)B * U;    // [B][U]: LSTM dc carried to the previous step
-  float *dhz = dcs + (size_t)B * U;      // [B][U]: GRU z * dh (direct path)
+  float *xs = WT + (size_t)U * Gp;       // [2][BS][KCP]: staged columns of dR_t (double buffer)
+  float *part = xs + 2 * (size_t)BS * KCP;  // [KS][BS][U]: K-slice partial sums
+  float *dhrec = part + (size_t)KS * BS * U;  // [BS][U]: W_hh^T dR part of dh_t (+ direct GRU path)
+  float *dcs = dhrec + (size_t)BS * U;   // [BS][U]: LSTM dc carried to the previous step
+  float *dhz = dcs + (size_t)BS * U;     // [BS][U]: GRU z * dh (direct path)
+  unsigned *ctr = p.ctr + bgi;
   const int tid = threadIdx.x;
   for (int e = tid; e < U * Gp; e += NT) {
     const int j = e / Gp, n = e % Gp;
     WT[e] = (j < nu && n < G) ? p.Whh[(size_t)n * p.ldw + u0 + j] : 0.f;
   }
-  for (int e = tid; e < B * U; e += NT) {
+  for (int e = tid; e < BS * U; e += NT) {
     const int b = e / U, j = e % U;
-    const bool ok = j < nu;
-    dhrec[e] = (ok && p.dhn) ? p.dhn[(size_t)b * H + u0 + j] : 0.f;
-    dcs[e] = (ok && lstm && p.dcn) ? p.dcn[(size_t)b * H + u0 + j] : 0.f;
+    const bool ok = j < nu && b < Bl;
+    dhrec[e] = (ok && p.dhn) ? p.dhn[(size_t)(b0 + b) * H + u0 + j] : 0.f;
+    dcs[e] = (ok && lstm && p.dcn) ? p.dcn[(size_t)(b0 + b) * H + u0 + j] : 0.f;
     dhz[e] = 0.f;
   }
   __syncthreads();
   const bool vec = (G & 3) == 0;
-  const int RG = ceil_div(B, 4);
+  const int RG = ceil_div(Bl, 4);
   for (int t = p.T - 1, it = 1; t >= 0; --t, ++it) {
     // ---- gate gradients of this CTA's units at step t
-    for (int e = tid; e < B * U; e += NT) {
-      const int b = e / U, j = e % U;
+    for (int e = tid; e < Bl * U; e += NT) {
+      const int bl = e / U, j = e % U;
       if (j >= nu) continue;
-      const int u = u0 + j;
+      const int u = u0 + j, b = b0 + bl;
       const size_t r = (size_t)t * B + b;
       const float dh = p.dy[r * H + u] + dhrec[e];
       const float *g = p.gates + r * G;
@@ -157,7 +163,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
       }
     }
     // every CTA's gate gradients of step t are published
-    if (!group_barrier(p.ctr, (unsigned)it * gridDim.x, p.err, p.timeout_ns)) return;
+    if (!group_barrier(ctr, (unsigned)it * p.NUG, p.err, p.timeout_ns)) return;
     // ---- dh_{t-1} of this CTA's units: W_hh^T dR_t (+ z dh).  dR_t is staged
     // in chunks of KC columns with coalesced loads; thread (row group of 4,
     // K slice) keeps a 4 x U register tile and walks the chunk's float4
@@ -176,10 +182,10 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
     // aligned (G a multiple of 4), else plain loads
     auto stage = [&](int c) {
       const int k0 = c * KC, kc4 = min(KC, Gp - k0) >> 2;
-      float *xb = xs + (size_t)(c & 1) * B * KCP;
-      for (int e = tid; e < B * kc4; e += NT) {
+      float *xb = xs + (size_t)(c & 1) * BS * KCP;
+      for (int e = tid; e < Bl * kc4; e += NT) {
         const int b = e / kc4, q = e % kc4, k = k0 + 4 * q;
-        const float *src = drt + (size_t)b * G + k;
+        const float *src = drt + (size_t)(b0 + b) * G + k;
         float *dst = xb + (size_t)b * KCP + 4 * q;
         if (vec) {
           cp_async16(dst, src);
@@ -204,14 +210,14 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
       }
       __syncthreads();
       const int k0 = c * KC, kc4 = min(KC, Gp - k0) >> 2;
-      const float *xb = xs + (size_t)(c & 1) * B * KCP;
+      const float *xb = xs + (size_t)(c & 1) * BS * KCP;
       if (comp) {
         for (int q = ksl; q < kc4; q += KS) {
           float4 x[4];
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             const int b = 4 * rg + r;
-            x[r] = b < B ? *reinterpret_cast<const float4 *>(xb + (size_t)b * KCP + 4 * q)
+            x[r] = b < Bl ? *reinterpret_cast<const float4 *>(xb + (size_t)b * KCP + 4 * q)
                          : make_float4(0.f, 0.f, 0.f, 0.f);
           }
 #pragma unroll
@@ -231,25 +237,25 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int b = 4 * rg + r;
-        if (b >= B) break;
+        if (b >= Bl) break;
 #pragma unroll
         for (int j = 0; j < UMAX; ++j)
-          if (j < U) part[((size_t)ksl * B + b) * U + j] = acc[r][j];
+          if (j < U) part[((size_t)ksl * BS + b) * U + j] = acc[r][j];
       }
     }
     __syncthreads();
-    for (int e = tid; e < B * U; e += NT) {
+    for (int e = tid; e < Bl * U; e += NT) {
       float v = 0.f;
-      for (int q = 0; q < KS; ++q) v += part[(size_t)q * B * U + e];
+      for (int q = 0; q < KS; ++q) v += part[(size_t)q * BS * U + e];
       dhrec[e] = (lstm ? 0.f : dhz[e]) + v;
     }
     __syncthreads();
   }
-  for (int e = tid; e < B * U; e += NT) {
+  for (int e = tid; e < Bl * U; e += NT) {
     const int b = e / U, j = e % U;
     if (j >= nu) continue;
-    if (p.dh0) p.dh0[(size_t)b * H + u0 + j] = dhrec[e];
-    if (lstm && p.dc0) p.dc0[(size_t)b * H + u0 + j] = dcs[e];
+    if (p.dh0) p.dh0[(size_t)(b0 + b) * H + u0 + j] = dhrec[e];
+    if (lstm && p.dc0) p.dc0[(size_t)(b0 + b) * H + u0 + j] = dcs[e];
   }
 }
 
@@ -290,27 +296,43 @@ __global__ void colsum_final_kernel(const float *__restrict__ part, int chunks, 
   out[n] = s;
 }
 
-struct RecPlan { int U, Gp, KC, KS; size_t smem; };
-size_t rec_smem(int U, int Gp, int B, int KC, int KS) {
-  return ((size_t)U * Gp + 2 * (size_t)B * (KC + 4) + (size_t)KS * B * U + 3 * (size_t)B * U) *
+struct RecPlan { int U, Gp, KC, KS, BS, NUG, NBG; size_t smem; };
+size_t rec_smem(int U, int Gp, int BS, int KC, int KS) {
+  return ((size_t)U * Gp + 2 * (size_t)BS * (KC + 4) + (size_t)KS * BS * U + 3 * (size_t)BS * U) *
          sizeof(float);
 }
-// U = units per CTA (one CTA per SM at most), K slices so that (row groups of
-// 4) x slices fill the CTA, chunk width KC (a multiple of 4 * KS) as large as
-// shared memory allows, at most 512 columns
+// The grid is NBG batch groups x NUG unit groups (at most one CTA per SM: the
+// launch is cooperative).  Every CTA streams its rows of dR_t from L2 each
+// step, NBG * NUG * BS * G floats in all, so more units per CTA (fewer unit
+// groups) means less traffic: the batch is split as far as the register tile
+// (UMAX units) and shared memory (W_hh^T columns, staged chunks of at least
+// 4 * KS columns) allow.  KC: chunk width, a multiple of 4 * KS, at most 512.
 RecPlan plan_rec(int H, int B, int nG, int nsm) {
-  RecPlan r{};
-  r.U = std::max(1, ceil_div(H, nsm));
-  r.Gp = round_up(nG * H, 4);
-  const int RG = ceil_div(B, 4);
-  r.KS = std::max(1, std::min(32, NT / RG));
-  if (r.U > UMAX || RG > NT) return RecPlan{};
-  r.KC = std::min(512, round_up(r.Gp, 4 * r.KS));
-  while (r.KC > 4 * r.KS && rec_smem(r.U, r.Gp, B, r.KC, r.KS) > (size_t)227 * 1024)
-    r.KC -= 4 * r.KS;
-  r.smem = rec_smem(r.U, r.Gp, B, r.KC, r.KS);
-  if (r.smem > (size_t)227 * 1024) return RecPlan{};
-  return r;
+  RecPlan best{};
+  long long best_traffic = -1;
+  for (int nbg = 1; nbg <= 8 && nbg <= ceil_div(B, 4); nbg *= 2) {
+    RecPlan r{};
+    r.NBG = nbg;
+    r.BS = ceil_div(B, nbg);
+    const int per = std::max(1, std::min(H, nsm / nbg));
+    r.U = ceil_div(H, per);
+    r.NUG = ceil_div(H, r.U);
+    r.Gp = round_up(nG * H, 4);
+    const int RG = ceil_div(r.BS, 4);
+    if (r.U > UMAX || RG > NT || r.NUG * nbg > nsm) continue;
+    r.KS = std::max(1, std::min(32, NT / RG));
+    r.KC = std::min(512, round_up(r.Gp, 4 * r.KS));
+    while (r.KC > 4 * r.KS && rec_smem(r.U, r.Gp, r.BS, r.KC, r.KS) > (size_t)227 * 1024)
+      r.KC -= 4 * r.KS;
+    r.smem = rec_smem(r.U, r.Gp, r.BS, r.KC, r.KS);
+    if (r.smem > (size_t)227 * 1024) continue;
+    const long long traffic = (long long)nbg * r.NUG * r.BS;
+    if (best_traffic < 0 || traffic < best_traffic) {
+      best = r;
+      best_traffic = traffic;
+    }
+  }
+  return best;
 }
 
 }  // namespace
@@ -331,7 +353,7 @@ cudaError_t launch_bwd_rec(const BwdRecArgs &a, int nsm, cudaStream_t s) {
   const int U = rp.U;
   BwdParams p{};
   p.T = a.T; p.B = a.B; p.H = a.H; p.cell = a.cell; p.U = U;
-  p.Gp = rp.Gp; p.KC = rp.KC; p.KS = rp.KS;
+  p.Gp = rp.Gp; p.KC = rp.KC; p.KS = rp.KS; p.BS = rp.BS; p.NUG = rp.NUG;
   p.Whh = a.Whh; p.ldw = a.ldw;
   p.gates = a.gates; p.zh = a.zh; p.cs = a.cs; p.c0 = a.c0; p.hp = a.hp;
   p.dy = a.dy; p.dhn = a.dhn; p.dcn = a.dcn;
@@ -342,7 +364,7 @@ cudaError_t launch_bwd_rec(const BwdRecArgs &a, int nsm, cudaStream_t s) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   void *args[] = {&p};
-  return cudaLaunchCooperativeKernel((const void *)bwd_rec_kernel, dim3(ceil_div(a.H, U)),
+  return cudaLaunchCooperativeKernel((const void *)bwd_rec_kernel, dim3(rp.NBG * rp.NUG),
                                      dim3(NT), args, smem, s);
 }
 
