@@ -400,7 +400,8 @@ RCU_API int rssm_unroll(rcu_rssm_t h, int T, int B, const float *state0, const f
 
 RCU_API int rssm_get_status(rcu_rssm_t h, void *stream);
 
-/* Attributes of an RSSM handle: RCU_ATTR_TRACE (1 = record per-step stamps). */
+/* Attributes of an RSSM handle: RCU_ATTR_TRACE (1 = record per-step stamps),
+ * RCU_ATTR_BARRIER_TIMEOUT_NS (bound on each wait for a broadcast vector). */
 RCU_API int rssm_set_attr(rcu_rssm_t h, int attr, int64_t value);
 
 /*

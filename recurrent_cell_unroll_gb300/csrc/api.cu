@@ -1217,7 +1217,8 @@ struct rcu_rssm_s {
   int Hx = 0;
   DevBuf Wa1, ba1, Wa2, ba2;
   int launches = 0;
-  DevBuf ctl;
+  DevBuf ctl;  // device error word
+  int64_t timeout_ns = 2000000000LL;  // bound on each wait for a broadcast vector
   bool trace = false;
   DevBuf trace_buf;
   int trace_T = 0;
@@ -1227,6 +1228,11 @@ struct rcu_rssm_s {
 
 extern "C" int rssm_set_attr(rcu_rssm_t h, int attr, int64_t value) {
   if (!h) return fail(RCU_ERR_INVALID, "rssm_set_attr: NULL handle");
+  if (attr == RCU_ATTR_BARRIER_TIMEOUT_NS) {
+    if (value <= 0) return fail(RCU_ERR_INVALID, "timeout must be > 0");
+    h->timeout_ns = value;
+    return RCU_OK;
+  }
   if (attr != RCU_ATTR_TRACE) return fail(RCU_ERR_INVALID, "rssm_set_attr: unknown attribute %d", attr);
   h->trace = value != 0;
   return RCU_OK;
@@ -1338,6 +1344,8 @@ static int rssm_run(rcu_rssm_t h, bool with_actor, int T, int B, const float *st
     p.Wa2 = (const float *)h->Wa2.p; p.ba2 = (const float *)h->ba2.p;
     p.actions_out = actions_out;
   }
+  p.err = (int *)h->ctl.p;
+  p.timeout_ns = (uint64_t)h->timeout_ns;
   p.trace = nullptr;
   if (h->trace) {
     CU(h->trace_buf.ensure((size_t)T * 16 * 8));
@@ -1415,7 +1423,10 @@ extern "C" int rssm_get_status(rcu_rssm_t h, void *stream) {
   if (!h) return fail(RCU_ERR_INVALID, "rssm_get_status: NULL handle");
   CU(cudaStreamSynchronize((cudaStream_t)stream));
   CU(cudaGetLastError());
-  return RCU_OK;
+  int v = 0;
+  CU(cudaMemcpy(&v, h->ctl.p, sizeof v, cudaMemcpyDeviceToHost));
+  CU(cudaMemset(h->ctl.p, 0, sizeof v));
+  return status_from_dev(v);
 }
 
 extern "C" int rssm_last_launch_count(rcu_rssm_t h) { return h ? h->launches : -1; }

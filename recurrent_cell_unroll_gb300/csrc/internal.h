@@ -112,6 +112,8 @@ struct RssmParams {
   const float *state0, *belief0, *actions, *eps;
   float *means, *stds, *states, *beliefs;
   unsigned long long *trace;  // NULL, or [T][16] stamps written by CTA 0 (see rssm_get_trace)
+  int *err;                   // device error word (DEV_TIMEOUT when a bounded wait gave up)
+  uint64_t timeout_ns;        // bound on each wait for a broadcast vector
   // unroll variant 2: Wa1 != NULL computes each step's action as
   // tanh(Wa2 ELU(Wa1 [state, belief] + ba1) + ba2) (Wa1 [Hx, S+RH], Wa2 [A, Hx]);
   // actions_out [T,B,A] receives them (may be NULL); `actions` is unused

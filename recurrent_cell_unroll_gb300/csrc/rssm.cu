@@ -12,16 +12,21 @@
 // shared memory (transposed, [k][o]).  Each phase is a batched mat-vec over
 // the cluster's batch rows spread across all threads of the CTA as
 // (output, row, K-chunk); the chunk partials are summed from shared memory,
-// and the CTA's output slice is broadcast into every CTA's shared memory
-// through distributed shared memory, followed by a cluster barrier (a
-// hardware barrier: it cannot hang and needs no timeout).  Clusters take
-// disjoint batch slices and never wait on each other.
+// and the CTA's output slice is broadcast into every CTA's shared memory with
+// asynchronous distributed-shared-memory stores (st.async), each counting its
+// bytes on the receiving CTA's mbarrier for that vector.  A CTA starts the
+// next phase as soon as all bytes of the vector it needs have landed: no
+// cluster-wide barrier and no release fence per phase.  A CTA can finish
+// phase k+1 only after every CTA has sent its phase-k output (after reading
+// its phase-k inputs), so no vector is overwritten while a peer still reads
+// it.  Clusters take disjoint batch slices and never wait on each other.
 #include <cooperative_groups.h>
 
 #include <algorithm>
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc_common.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -34,7 +39,7 @@ constexpr int NT = 512;
 constexpr int MAXBC = 8; // batch rows per cluster
 constexpr int KS_MAX = 16;
 constexpr size_t PRELOAD_MAX = 32 * 1024;  // bytes of actions+eps kept in shared memory
-constexpr size_t SMEM_CAP = 227 * 1024;    // dynamic shared memory per CTA
+constexpr size_t SMEM_CAP = 227 * 1024 - 64;  // dynamic shared memory per CTA (64 B static)
 
 __host__ __device__ inline int r4(int v) { return (v + 3) & ~3; }
 
@@ -211,21 +216,16 @@ __device__ __forceinline__ void load_T(const float *src, int K, int row0, int n,
   }
 }
 
-// Split cluster barrier: stores placed between arrive and wait are not
-// ordered by this arrival's release (they are outputs nobody in the cluster
-// reads), so the release does not wait for them.
-__device__ __forceinline__ void cl_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+// 4-byte asynchronous store into cluster CTA shared memory (address from
+// mapa), completing as 4 bytes of complete_tx on that CTA's mbarrier
+__device__ __forceinline__ void st_async_b32(uint32_t addr, float v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                   addr),
+               "r"(__float_as_uint(v)), "r"(bar)
+               : "memory");
 }
-__device__ __forceinline__ void cl_wait() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void flush_outputs(float (&v)[3], float *(&ptr)[3], int n) {
-  for (int i = 0; i < n; ++i) {
-    if (ptr[i]) *ptr[i] = v[i];
-    ptr[i] = nullptr;
-  }
-}
+// the broadcast vectors, one mbarrier each
+enum Vec { V_ST = 0, V_HX, V_ACT, V_AV, V_BEL, V_QV, NVEC };
 
 // part[0][r][o] = sum over q of part[q][r][o], spread over all threads (the
 // consumers then read one value per output instead of ks).  Callers
@@ -326,12 +326,54 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
       sm[L.eps + e] = r < nr ? p.eps[((size_t)t * p.B + b0 + r) * S + k] : 0.f;
     }
   }
+  __shared__ uint64_t vbar[NVEC];
+  __shared__ int s_ok;
+  if (tid == 0) {
+    for (int v = 0; v < NVEC; ++v) tc::mbar_init(&vbar[v], 1);
+    tc::fence_mbar_init();
+  }
+  // every CTA's vectors are initialised and its mbarriers exist before any
+  // peer sends
   cluster.sync();
   if (tr) p.trace[12] = globaltimer_ns();
 
-  float *rem[RC];
+  // shared-memory window of each cluster CTA, and its mbarriers
+  const uint32_t sm0 = (uint32_t)__cvta_generic_to_shared(sm);
+  uint32_t rsm[RC], rbar[RC];
 #pragma unroll
-  for (int r = 0; r < RC; ++r) rem[r] = cluster.map_shared_rank(sm, r);
+  for (int r = 0; r < RC; ++r) {
+    rsm[r] = tc::mapa_shared(sm0, (uint32_t)r);
+    rbar[r] = tc::mapa_shared((uint32_t)__cvta_generic_to_shared(&vbar[0]), (uint32_t)r);
+  }
+  // send value v to float offset `off` of every CTA, counted on vector `vec`
+  auto bcast = [&](size_t off, float v, int vec) {
+#pragma unroll
+    for (int r = 0; r < RC; ++r)
+      st_async_b32(rsm[r] + (uint32_t)(off * 4), v, rbar[r] + (uint32_t)(vec * 8));
+  };
+  // bytes each CTA receives per use of each vector
+  uint32_t vbytes[NVEC];
+  vbytes[V_ST] = (uint32_t)(Bc * S * 4);
+  vbytes[V_HX] = (uint32_t)(Bc * (actor ? d.Hx : 0) * 4);
+  vbytes[V_ACT] = (uint32_t)(Bc * A * 4);
+  vbytes[V_AV] = (uint32_t)(Bc * Hd * 4);
+  vbytes[V_BEL] = (uint32_t)(Bc * RH * 4);
+  vbytes[V_QV] = (uint32_t)(Bc * Hd * 4);
+  uint32_t uses = 0;  // thread 0: completed uses per vector, 4 bits each
+  volatile int abort_ = 0;
+  const uint64_t tmo = p.timeout_ns;
+  // wait until vector `vec` of this use has fully landed (bounded)
+  auto wait_vec = [&](int vec) -> bool {
+    if (tid == 0) {
+      const uint32_t n = (uses >> (4 * vec)) & 15u;
+      tc::mbar_arrive_expect_tx(&vbar[vec], vbytes[vec]);
+      s_ok = tc::mbar_wait(&vbar[vec], n & 1u, p.err, &abort_, tmo);
+      uses = (uses & ~(15u << (4 * vec))) | (((n + 1) & 15u) << (4 * vec));
+    }
+    __syncthreads();
+    return s_ok != 0;
+  };
+  bool ok = true;
 
   const int ks1 = split_of(d.Hap, SA);
   const int ks2a = split_of(d.U3p, Hd), ks2b = split_of(d.U3p, RH);
@@ -339,11 +381,11 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
   const int ks4 = split_of(d.S2p, Hd);
   const int ksx1 = actor ? split_of(d.Hxap, S + RH) : 1, ksx2 = actor ? split_of(d.Axap, d.Hx) : 1;
   float *part1 = sm + L.part1, *part2 = sm + L.part2;
-  float out_v[3] = {0.f, 0.f, 0.f};
-  float *out_p[3] = {nullptr, nullptr, nullptr};
 
   for (int t = 0; t < p.T; ++t) {
     const int cur = t & 1;
+    // the state of step t-1 (broadcast at the end of its phase 4)
+    if (t > 0 && !(ok = wait_vec(V_ST))) break;
     if (tr) p.trace[t * 16 + 0] = globaltimer_ns();
     float *bel_cur = sm + L.bel + (size_t)cur * Bc * RHp;
     const size_t bel_nxt = L.bel + (size_t)(cur ^ 1) * Bc * RHp;
@@ -363,10 +405,9 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
       for (int e = tid; e < nx * Bc; e += NT) {
         const int o = e % nx, r = e / nx;
         const float xv = elu_f(part_sum(part1, d.Hxap, r, o) + sm[L.ba1 + o]);
-#pragma unroll
-        for (int q2 = 0; q2 < RC; ++q2) rem[q2][L.hx + (size_t)r * d.Hxp + x0 + o] = xv;
+        bcast(L.hx + (size_t)r * d.Hxp + x0 + o, xv, V_HX);
       }
-      cluster.sync();
+      if (!(ok = wait_vec(V_HX))) break;
       // ---- actor, output: action = tanh(Wa2 x + ba2), owned entries, placed
       //      straight into every CTA's phase-1 input row
       matvec_part<NR>(sm + L.wa2, d.Axap, d.Hx, sm + L.hx, d.Hxp, ksx2, part1);
@@ -376,11 +417,10 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
       for (int e = tid; e < na * Bc; e += NT) {
         const int j = e % na, r = e / na;
         const float av = tanh_f(part_sum(part1, d.Axap, r, j) + sm[L.ba2 + j]);
-#pragma unroll
-        for (int q2 = 0; q2 < RC; ++q2) rem[q2][L.in1 + (size_t)r * SAp + S + a0 + j] = av;
+        bcast(L.in1 + (size_t)r * SAp + S + a0 + j, av, V_ACT);
         if (r < nr && p.actions_out) p.actions_out[((size_t)t * p.B + b0 + r) * A + a0 + j] = av;
       }
-      cluster.sync();
+      if (!(ok = wait_vec(V_ACT))) break;
       if (tr) p.trace[t * 16 + 5] = globaltimer_ns();
     }
     // ---- phase 1: a = ELU(W1 [state, action] + b1), owned outputs (with the
@@ -403,10 +443,9 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
     for (int e = tid; e < ni * Bc; e += NT) {
       const int o = e % ni, r = e / ni;
       const float a = elu_f(part_sum(part1, d.Hap, r, o) + sm[L.b1 + o]);
-#pragma unroll
-      for (int x = 0; x < RC; ++x) rem[x][L.av + (size_t)r * Hdp + i0 + o] = a;
+      bcast(L.av + (size_t)r * Hdp + i0 + o, a, V_AV);
     }
-    cluster.sync();
+    if (!(ok = wait_vec(V_AV))) break;
     if (tr) p.trace[t * 16 + 1] = globaltimer_ns();
     // ---- phase 2: GRUCell(a, belief) for owned units
     const long long c2 = clock64();
@@ -434,18 +473,11 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
       const float zg = sigmoid_f(gi[1] + gh[1]);
       const float ng = tanh_f(gi[2] + rg * gh[2]);
       const float hb = (1.f - zg) * ng + zg * bel_cur[(size_t)r * RHp + j0 + j];
-#pragma unroll
-      for (int x = 0; x < RC; ++x) rem[x][bel_nxt + (size_t)r * RHp + j0 + j] = hb;
-      if (r < nr) {
-        float *dst = p.beliefs + ((size_t)t * p.B + b0 + r) * RH + j0 + j;
-        if (e == tid) { out_v[0] = hb; out_p[0] = dst; }  // stored after the arrival
-        else *dst = hb;
-      }
+      bcast(bel_nxt + (size_t)r * RHp + j0 + j, hb, V_BEL);
+      if (r < nr) p.beliefs[((size_t)t * p.B + b0 + r) * RH + j0 + j] = hb;
     }
     if (tr) p.trace[t * 16 + 9] = clock64() - c2;
-    cl_arrive();
-    flush_outputs(out_v, out_p, 1);
-    cl_wait();
+    if (!(ok = wait_vec(V_BEL))) break;
     if (tr) p.trace[t * 16 + 2] = globaltimer_ns();
     // ---- phase 3: q = ELU(W2 belief + b2), owned outputs
     matvec_part<NR>(sm + L.w2, d.Hap, RH, sm + bel_nxt, RHp, ks3, part1);
@@ -455,10 +487,9 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
     for (int e = tid; e < ni * Bc; e += NT) {
       const int o = e % ni, r = e / ni;
       const float qv = elu_f(part_sum(part1, d.Hap, r, o) + sm[L.b2 + o]);
-#pragma unroll
-      for (int x = 0; x < RC; ++x) rem[x][L.qv + (size_t)r * Hdp + i0 + o] = qv;
+      bcast(L.qv + (size_t)r * Hdp + i0 + o, qv, V_QV);
     }
-    cluster.sync();
+    if (!(ok = wait_vec(V_QV))) break;
     if (tr) p.trace[t * 16 + 3] = globaltimer_ns();
     // ---- phase 4: p = W3 q + b3 -> mean, std, sampled state (owned entries)
     matvec_part<NR>(sm + L.w3, d.S2p, Hd, sm + L.qv, Hdp, ks4, part1);
@@ -475,23 +506,27 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
         const size_t o = ((size_t)t * p.B + b0 + r) * S + s0 + j;
         const float ev = L.preload ? sm[L.eps + ((size_t)t * Bc + r) * S + s0 + j] : __ldg(p.eps + o);
         st = fmaf(ev, sd, mean);
-        if (e == tid) {  // stored after the arrival
-          out_v[0] = mean; out_p[0] = p.means + o;
-          out_v[1] = sd; out_p[1] = p.stds + o;
-          out_v[2] = st; out_p[2] = p.states + o;
-        } else {
-          p.means[o] = mean;
-          p.stds[o] = sd;
-          p.states[o] = st;
-        }
+        p.means[o] = mean;
+        p.stds[o] = sd;
+        p.states[o] = st;
       }
-#pragma unroll
-      for (int x = 0; x < RC; ++x) rem[x][L.st + (size_t)r * S + s0 + j] = st;
+      // the last step's state feeds no further step: not sent
+      if (t + 1 < p.T) bcast(L.st + (size_t)r * S + s0 + j, st, V_ST);
     }
-    cl_arrive();
-    flush_outputs(out_v, out_p, 3);
-    cl_wait();
+    if (p.trace) __syncthreads();  // (trace only: this CTA's phase 4 is done)
     if (tr) p.trace[t * 16 + 4] = globaltimer_ns();
+  }
+  // On a normal exit every byte sent to this CTA has been waited for.  After
+  // a failed wait, peers may still be sending: every CTA leaves its loop (a
+  // bounded wait or the error word ends each one), then the whole cluster
+  // meets, and each CTA gives stores already issued time to land before its
+  // shared memory goes away.
+  if (!ok && tid == 0) atomicCAS(p.err, DEV_OK, DEV_TIMEOUT);
+  cluster.sync();
+  if (!ok || ld_volatile_int(p.err) != DEV_OK) {
+    const uint64_t until = globaltimer_ns() + 20000;  // 20 us
+    while (globaltimer_ns() < until) {
+    }
   }
 }
 
