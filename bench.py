@@ -352,8 +352,33 @@ def make_train_runner(spec, inp, dev, net, d):
     return step, launches, profile_on, profile_read, e2e_io, status, net
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each
+# workload's dominant kernel, from single-pass ncu captures of the full-size
+# workloads (the mean over the captured launches); a kernel changed after its
+# capture must be taken out of this table (its traffic is then null).
+TRAFFIC = {
+    ("gru_bf16_3L_T512_B256_1024", "recurrent_tc"): 1.962e9,
+    ("lstmp_bf16_2L_T1000_B32_80x1024p256", "recurrent_tc_lstmp"): 590.0e6,
+    ("bilstm_f32_varlen_B64_T500_256x512", "recurrent_simt"): 357.9e6,
+    ("lstm_f32_T80_B1_512x256", "recurrent_cluster"): 1.41e6,
+    ("rssm_f32_B50_T50_S20_A6_H200", "rssm_unroll"): 1.57e6,
+    ("rssm_actor_f32_B50_T50_S20_A6_H200_X200", "rssm_unroll"): 1.71e6,
+    ("lstm_train_f32_T500_B64_256x512", "bwd_recurrent"): 630.8e6,
+}
+
+
 def roofline(spec, inp, prof, peaks, nsm, step_ms=None):
     """Roofline of the dominant kernel from the live event timings."""
+    r = _roofline(spec, inp, prof, peaks, nsm, step_ms)
+    if r is not None:
+        tr = TRAFFIC.get((spec.name, r["kernel"]))
+        r["traffic"] = tr
+        if tr is not None:
+            r["traffic_unit"] = "bytes per launch (ncu dram read + write)"
+    return r
+
+
+def _roofline(spec, inp, prof, peaks, nsm, step_ms=None):
     if isinstance(spec, wl.RssmSpec):
         # one kernel per step: its launch time is the event-timed step
         per_launch = kernel_flops(spec, inp)["rssm"][0]
