@@ -884,6 +884,18 @@ static int forward_host_chunked(rcu_rnn_t h, int T, int B, int n, const float *x
   const void *dh0, *dc0;
   CU(io.in(h0, LDB * h->Hout * 4, h->io_h0, false, &dh0));
   CU(io.in(c0, LDB * h->H * 4, h->io_c0, false, &dc0));
+  // an early return (an error) must not leave copies of the caller's host
+  // buffers in flight on the handle's streams
+  struct DrainOnError {
+    cudaStream_t a, b;
+    bool armed = true;
+    ~DrainOnError() {
+      if (armed) {
+        cudaStreamSynchronize(a);
+        cudaStreamSynchronize(b);
+      }
+    }
+  } drain{h->cp_in, h->cp_out};
   // the copy streams start after the work already on s
   CU(cudaEventRecord(ev_entry, s));
   CU(cudaStreamWaitEvent(h->cp_in, ev_entry, 0));
@@ -923,6 +935,7 @@ static int forward_host_chunked(rcu_rnn_t h, int T, int B, int n, const float *x
   const int kl = (n - 1) & 1;
   if (h_n) CU(cudaMemcpyAsync(h_n, h->io_st[kl].p, LDB * h->Hout * 4, cudaMemcpyDefault, s));
   if (c_n) CU(cudaMemcpyAsync(c_n, h->io_ct[kl].p, LDB * h->H * 4, cudaMemcpyDefault, s));
+  drain.armed = false;  // s now waits for every copy
   h->launches = launches;
   return RCU_OK;
 }
