@@ -577,6 +577,26 @@ def test_forward_host_equals_device(spec, pinned):
     net.close()
 
 
+def test_forward_host_single_step_and_tiny_batch():
+    """T = 1 (one chunk whatever the attribute) and B = 1 through the host call."""
+    for spec in (HOST_SPECS[1].scaled(T=1, B=1), HOST_SPECS[0].scaled(T=1, B=2)):
+        inp = wl.make_rnn_inputs(spec, seed=8)
+        ref = run_gpu(spec, inp)
+        net = binding.RNN.from_spec(spec)
+        net.set_attr(binding.RCU_ATTR_HOST_CHUNKS, 4)
+        net.set_weights(inp["weights"])
+        x, L, h0, c0 = _host_inputs(spec, inp, True)
+        LD = spec.layers * spec.D
+        y = torch.empty((spec.T, spec.B, spec.D * spec.Hout)).pin_memory()
+        hn = torch.empty((LD, spec.B, spec.Hout)).pin_memory()
+        cn = torch.empty((LD, spec.B, spec.hidden)).pin_memory() if spec.cell == "lstm" else None
+        binding.rnn_forward_host(net.h, spec.T, spec.B, x, L, h0, c0, y, hn, cn)
+        torch.cuda.synchronize()
+        assert net.status() == 0
+        assert np.array_equal(y.numpy(), ref[0]) and np.array_equal(hn.numpy(), ref[1])
+        net.close()
+
+
 @pytest.mark.parametrize("chunks", [2, 3, 16])
 @pytest.mark.parametrize("spec", [HOST_SPECS[1], HOST_SPECS[0], HOST_SPECS[3],
                                   HOST_SPECS[2]], ids=lambda s: s.name)
@@ -686,6 +706,8 @@ BWD_SPECS = [
     wl.GRU_3L.scaled(T=5, B=3, in_dim=7, hidden=13, layers=1, dtype="f32", h0_std=0.3),
     wl.LSTM_T80.scaled(T=32, B=64, in_dim=256, hidden=512, layers=1),
     wl.GRU_3L.scaled(T=24, B=32, in_dim=128, hidden=256, layers=3, dtype="f32", h0_std=0.1),
+    wl.LSTM_T80.scaled(T=1, B=1, in_dim=5, hidden=7, layers=2, c0_std=0.5, h0_std=0.5),
+    wl.GRU_3L.scaled(T=9, B=130, in_dim=40, hidden=48, layers=1, dtype="f32", h0_std=0.0),
 ]
 
 
