@@ -190,6 +190,10 @@ struct rcu_rnn_s {
   DevBuf ws;
   Meta meta{};
   int ws_T = -1, ws_B = -1;
+  // (T, B, stream) whose fixed-length metadata (identity sort, full batch
+  // sizes) h->meta holds, so a repeated fixed-length forward skips the sort
+  int meta_T = -1, meta_B = -1;
+  cudaStream_t meta_s = nullptr;
   int last_T = -1, last_B = -1;
   char *xp = nullptr, *g = nullptr, *ymid = nullptr, *hx = nullptr, *mx = nullptr;
   char *mbuf = nullptr, *hx2 = nullptr;  // LSTMP tensor-core path
@@ -594,6 +598,7 @@ static int ensure_ws(rcu_rnn_s *h, int T, int B) {
     h->ytmp = (fold && h->layers > 1) ? (float *)(base + o_ytmp) : nullptr;
     h->ws_T = Tm;
     h->ws_B = Bm;
+    h->meta_T = h->meta_B = -1;  // the metadata moved
   }
   return RCU_OK;
 }
@@ -637,9 +642,14 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
     h->trace_T = T;
   }
   if (h->P > 0) CU(cudaMemsetAsync(h->mx, 0, (size_t)D * B * h->Hp * es, s));
-  h->begin("meta_sort", s);
-  CU(launch_meta(lengths, B, T, h->meta, err, s));
-  h->end(s);
+  if (varlen || T != h->meta_T || B != h->meta_B || s != h->meta_s) {
+    h->begin("meta_sort", s);
+    CU(launch_meta(lengths, B, T, h->meta, err, s));
+    h->end(s);
+    h->meta_T = varlen ? -1 : T;
+    h->meta_B = varlen ? -1 : B;
+    h->meta_s = s;
+  }
   if (varlen) {
     h->begin("zero_tail", s);
     CU(launch_zero_tail(y, lengths, T, B, D * Hout, err, s));

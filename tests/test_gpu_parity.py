@@ -529,6 +529,36 @@ def test_rssm_actor_errors():
     m0.close()
 
 
+def test_metadata_reuse_across_calls():
+    """One handle: fixed-length, variable-length, fixed-length again and another
+    T: the fixed-length metadata kept between calls is rebuilt whenever it no
+    longer describes the call, so every result matches the oracle."""
+    spec = wl.BILSTM_VAR.scaled(T=9, B=6, in_dim=8, hidden=12, bidir=False, varlen=(2, 9))
+    inp = wl.make_rnn_inputs(spec, seed=31)
+    dev = torch.device("cuda")
+    net = binding.RNN.from_spec(spec)
+    net.set_weights(inp["weights"])
+    x = inp["x"].to(dev)
+    ref_fixed = oracle.rnn_forward(oracle.LSTM, inp["x"], inp["weights"], hidden=spec.hidden)
+    ref_var = run_oracle(spec, inp)
+    ref_short = oracle.rnn_forward(oracle.LSTM, inp["x"][:5], inp["weights"], hidden=spec.hidden)
+    for kind in ("fixed", "var", "fixed", "fixed", "short", "fixed"):
+        if kind == "var":
+            y, hn, cn = net.forward(x, lengths=inp["lengths"].to(dev))
+            ref = ref_var
+        elif kind == "short":
+            y, hn, cn = net.forward(x[:5].contiguous())
+            ref = ref_short
+        else:
+            y, hn, cn = net.forward(x)
+            ref = ref_fixed
+        assert net.status() == 0
+        e = np.abs(y.cpu().numpy() - ref[0]).max()
+        assert e <= F32_TOL, f"{kind}: {e:.3e}"
+        assert np.abs(hn.cpu().numpy() - ref[1]).max() <= F32_TOL
+    net.close()
+
+
 # ----------------------------------------------------------------------------- host-buffer entry points
 
 HOST_SPECS = [
