@@ -146,7 +146,9 @@ def fp32_alu_peak_tflops(nsm: int, mhz: float) -> float:
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi clocks/throttle reasons sampled every 200 ms in the background."""
+    """nvidia-smi clocks/throttle reasons sampled every 50 ms in the background;
+    start() returns once the first sample has arrived, so samples fall inside
+    a timed region that begins after it."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -162,13 +164,17 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
             return
         self._t = threading.Thread(target=self._read, daemon=True)
         self._t.start()
+        deadline = time.time() + 3.0
+        while not self.lines and time.time() < deadline and self.proc.poll() is None:
+            time.sleep(0.01)
+        self.lines.clear()  # keep only samples taken from here on
 
     def _read(self):
         for ln in self.proc.stdout:
