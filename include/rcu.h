@@ -69,8 +69,12 @@ typedef struct rcu_rssm_s *rcu_rssm_t;
 
 /* Attributes for rnn_set_attr / rssm_set_attr. */
 #define RCU_ATTR_BARRIER_TIMEOUT_NS 1 /* bound on any device wait (default 2e9 ns) */
-#define RCU_ATTR_TEST_DROP_ARRIVAL 2  /* testing only: 1 = one CTA never arrives at the
-                                         first step barrier, so the wait must time out */
+#define RCU_ATTR_TEST_DROP_ARRIVAL 2  /* testing only: 1 = one CTA of the forward's first
+                                         recurrent kernel never arrives at the first step
+                                         barrier, 2 = the same in the backward recurrence
+                                         (rnn_backward); on an RSSM handle, nonzero = one CTA
+                                         skips its first state broadcast.  The waits must
+                                         time out (RCU_ERR_TIMEOUT from *_get_status). */
 #define RCU_ATTR_FORCE_PATH 3         /* 0 = automatic, 1 = portable SIMT kernels only,
                                          2 = tensor-core (tcgen05) kernels where supported,
                                          3 = cluster-resident recurrent kernel where W_hh

@@ -382,7 +382,10 @@ extern "C" int rnn_set_attr(rcu_rnn_t h, int attr, int64_t value) {
       if (value <= 0) return fail(RCU_ERR_INVALID, "timeout must be > 0");
       h->timeout_ns = value;
       return RCU_OK;
-    case RCU_ATTR_TEST_DROP_ARRIVAL: h->drop_arrival = value != 0; return RCU_OK;
+    case RCU_ATTR_TEST_DROP_ARRIVAL:
+      if (value < 0 || value > 2) return fail(RCU_ERR_INVALID, "drop arrival must be 0, 1 or 2");
+      h->drop_arrival = (int)value;
+      return RCU_OK;
     case RCU_ATTR_PROFILE:
       h->profile = value != 0;
       return RCU_OK;
@@ -725,7 +728,7 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
     p.ctr = ctr + (size_t)cstride * l;  // fresh counters per layer (zeroed above)
     p.err = err;
     p.timeout_ns = (uint64_t)h->timeout_ns;
-    p.drop_arrival = h->drop_arrival && l == 0;
+    p.drop_arrival = h->drop_arrival == 1 && l == 0;
     p.trace = (h->trace && l == 0) ? (unsigned long long *)h->trace_buf.p : nullptr;
     p.cclip = h->cclip;
     p.cclip_lo = h->cclip_lo;
@@ -1096,6 +1099,7 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
     a.dh0 = dh0 ? dh0 + (size_t)l * B * H : nullptr;
     a.dc0 = dc0 ? dc0 + (size_t)l * B * H : nullptr;
     a.ctr = ctr; a.err = err; a.timeout_ns = (uint64_t)h->timeout_ns;
+    a.drop_arrival = h->drop_arrival == 2 && l == L - 1;
     h->begin("bwd_recurrent", s);
     e = launch_bwd_rec(a, h->nsm, s);
     h->end(s);
@@ -1242,6 +1246,7 @@ struct rcu_rssm_s {
   int launches = 0;
   DevBuf ctl;  // device error word
   int64_t timeout_ns = 2000000000LL;  // bound on each wait for a broadcast vector
+  int drop_send = 0;                  // testing: RCU_ATTR_TEST_DROP_ARRIVAL
   bool trace = false;
   DevBuf trace_buf;
   int trace_T = 0;
@@ -1254,6 +1259,10 @@ extern "C" int rssm_set_attr(rcu_rssm_t h, int attr, int64_t value) {
   if (attr == RCU_ATTR_BARRIER_TIMEOUT_NS) {
     if (value <= 0) return fail(RCU_ERR_INVALID, "timeout must be > 0");
     h->timeout_ns = value;
+    return RCU_OK;
+  }
+  if (attr == RCU_ATTR_TEST_DROP_ARRIVAL) {
+    h->drop_send = value != 0;
     return RCU_OK;
   }
   if (attr != RCU_ATTR_TRACE) return fail(RCU_ERR_INVALID, "rssm_set_attr: unknown attribute %d", attr);
@@ -1369,6 +1378,7 @@ static int rssm_run(rcu_rssm_t h, bool with_actor, int T, int B, const float *st
   }
   p.err = (int *)h->ctl.p;
   p.timeout_ns = (uint64_t)h->timeout_ns;
+  p.drop_send = h->drop_send;
   p.trace = nullptr;
   if (h->trace) {
     CU(h->trace_buf.ensure((size_t)T * 16 * 8));

@@ -91,6 +91,7 @@ struct BwdParams {
   unsigned *ctr;
   int *err;
   uint64_t timeout_ns;
+  int drop_arrival;
 };
 
 __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
@@ -163,7 +164,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
       }
     }
     // every CTA's gate gradients of step t are published
-    if (!group_barrier(ctr, (unsigned)it * p.NUG, p.err, p.timeout_ns)) return;
+    if (!group_barrier(ctr, (unsigned)it * p.NUG, p.err, p.timeout_ns,
+                       p.drop_arrival && blockIdx.x == 0 && it == 1))
+      return;
     // ---- dh_{t-1} of this CTA's units: W_hh^T dR_t (+ z dh).  dR_t is staged
     // in chunks of KC columns with coalesced loads; thread (row group of 4,
     // K slice) keeps a 4 x U register tile and walks the chunk's float4
@@ -358,7 +361,7 @@ cudaError_t launch_bwd_rec(const BwdRecArgs &a, int nsm, cudaStream_t s) {
   p.gates = a.gates; p.zh = a.zh; p.cs = a.cs; p.c0 = a.c0; p.hp = a.hp;
   p.dy = a.dy; p.dhn = a.dhn; p.dcn = a.dcn;
   p.DA = a.DA; p.DR = a.DR; p.dh0 = a.dh0; p.dc0 = a.dc0;
-  p.ctr = a.ctr; p.err = a.err; p.timeout_ns = a.timeout_ns;
+  p.ctr = a.ctr; p.err = a.err; p.timeout_ns = a.timeout_ns; p.drop_arrival = a.drop_arrival;
   const size_t smem = rp.smem;
   cudaError_t e = cudaFuncSetAttribute((const void *)bwd_rec_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -114,6 +114,7 @@ struct RssmParams {
   unsigned long long *trace;  // NULL, or [T][16] stamps written by CTA 0 (see rssm_get_trace)
   int *err;                   // device error word (DEV_TIMEOUT when a bounded wait gave up)
   uint64_t timeout_ns;        // bound on each wait for a broadcast vector
+  int drop_send;              // testing: the first CTA of cluster 0 skips its step-0 state send
   // unroll variant 2: Wa1 != NULL computes each step's action as
   // tanh(Wa2 ELU(Wa1 [state, belief] + ba1) + ba2) (Wa1 [Hx, S+RH], Wa2 [A, Hx]);
   // actions_out [T,B,A] receives them (may be NULL); `actions` is unused
@@ -139,6 +140,7 @@ struct BwdRecArgs {
   unsigned *ctr;  // zeroed before the launch
   int *err;
   uint64_t timeout_ns;
+  int drop_arrival;  // testing: CTA 0 skips its first step arrival (the wait must run out)
 };
 // hidden units per CTA of the reverse-time kernel, 0 if W_hh^T does not fit
 int bwd_units_per_cta(int H, int B, int nG, int nsm);

@@ -511,7 +511,8 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
         p.states[o] = st;
       }
       // the last step's state feeds no further step: not sent
-      if (t + 1 < p.T) bcast(L.st + (size_t)r * S + s0 + j, st, V_ST);
+      if (t + 1 < p.T && !(p.drop_send && t == 0 && blockIdx.x == 0))
+        bcast(L.st + (size_t)r * S + s0 + j, st, V_ST);
     }
     if (p.trace) __syncthreads();  // (trace only: this CTA's phase 4 is done)
     if (tr) p.trace[t * 16 + 4] = globaltimer_ns();

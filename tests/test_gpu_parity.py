@@ -431,6 +431,51 @@ def test_barrier_timeout_on_tensor_core_path(ksplit):
     net.close()
 
 
+def test_backward_recurrence_timeout():
+    """A CTA of the reverse-time kernel skips its first step arrival: the
+    bounded counter wait runs out, the status reads RCU_ERR_TIMEOUT, and the
+    next backward on the same handle is correct."""
+    spec = BWD_SPECS[1]
+    inp = wl.make_rnn_inputs(spec, seed=15)
+    dy = torch.randn((spec.T, spec.B, spec.hidden), generator=torch.Generator().manual_seed(15))
+    dev = torch.device("cuda")
+    net = binding.RNN.from_spec(spec)
+    net.set_weights(inp["weights"])
+    net.set_attr(binding.RCU_ATTR_BARRIER_TIMEOUT_NS, 50_000_000)
+    net.set_attr(binding.RCU_ATTR_TEST_DROP_ARRIVAL, 2)
+    net.backward(inp["x"].to(dev), dy.to(dev), h0=inp["h0"].to(dev))
+    assert net.status() == binding.RCU_ERR_TIMEOUT
+    net.set_attr(binding.RCU_ATTR_TEST_DROP_ARRIVAL, 0)
+    dx, _, _, _ = net.backward(inp["x"].to(dev), dy.to(dev), h0=inp["h0"].to(dev))
+    assert net.status() == 0
+    ref = oracle.rnn_backward(oracle.GRU, inp["x"], inp["weights"], dy, hidden=spec.hidden,
+                              h0=inp["h0"])
+    assert _rel(dx.cpu().numpy(), ref["dx"]) <= BWD_REL
+    net.close()
+
+
+def test_rssm_broadcast_timeout():
+    """One CTA skips its first state broadcast: its cluster's bounded mbarrier
+    waits run out, rssm_get_status reads RCU_ERR_TIMEOUT, and the next unroll
+    on the same handle is correct."""
+    spec = wl.RSSM_B50.scaled(T=4, B=9)
+    inp = wl.make_rssm_inputs(spec, seed=16)
+    dev = torch.device("cuda")
+    m = binding.RSSM(spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden)
+    m.set_weights(inp["weights"])
+    binding.rssm_set_attr(m.h, binding.RCU_ATTR_BARRIER_TIMEOUT_NS, 50_000_000)
+    binding.rssm_set_attr(m.h, binding.RCU_ATTR_TEST_DROP_ARRIVAL, 1)
+    m.unroll(inp["actions"].to(dev), inp["eps"].to(dev))
+    assert binding.rssm_get_status(m.h) == binding.RCU_ERR_TIMEOUT
+    binding.rssm_set_attr(m.h, binding.RCU_ATTR_TEST_DROP_ARRIVAL, 0)
+    outs = m.unroll(inp["actions"].to(dev), inp["eps"].to(dev))
+    assert binding.rssm_get_status(m.h) == 0
+    ref = oracle.rssm_unroll(inp["weights"], inp["actions"], inp["eps"])
+    for o, r in zip(outs, ref):
+        assert np.abs(o.cpu().numpy() - r).max() <= F32_TOL
+    m.close()
+
+
 def test_two_handles_two_threads():
     import threading
     spec_a = wl.LSTM_T80.scaled(T=7, B=3, in_dim=9, hidden=33)
