@@ -104,3 +104,52 @@ def test_step_trace_medians():
     assert got == {"mat-vec": 10.0, "gates": 20.0, "h_t sent": 30.0}
     # phases whose stamps are absent are skipped
     assert step_trace._medians(tr, [(5, 6, "absent")]) == []
+
+
+def test_training_flops_are_forward_plus_bptt():
+    """forward 2MG(K+H); backward: recompute 2MG(K+H), dh recurrence 2MGH,
+    dW_ih + dW_hh 2MG(K+H), dx 2MGK (G = 4H for the LSTM)."""
+    spec = wl.LSTM_TRAIN
+    inp = wl.make_rnn_inputs(spec.scaled(T=2, B=2), seed=0)
+    inp["lengths"] = None
+    fl = bench.kernel_flops(spec, inp)
+    M, H, K = spec.B * spec.T, spec.hidden, spec.in_dim
+    G = 4 * H
+    assert fl["input_gemm"] == [2 * M * G * K] and fl["recurrent"] == [2 * M * G * H]
+    assert fl["bwd_recompute_gemm"] == [2 * M * G * (K + H)]
+    assert fl["bwd_recurrent"] == [2 * M * G * H]
+    assert fl["bwd_weight_gemm"] == [2 * M * G * (K + H)]
+    assert fl["bwd_dx_gemm"] == [2 * M * G * K]
+    assert "dy" in inp and inp["dy"].shape == (2, 2, H)
+
+
+def test_traffic_table_names_real_workloads_and_kernels():
+    """Every captured traffic entry belongs to a bench workload and to a kernel
+    name the roofline can report for it."""
+    names = {s.name for s in bench.WORKLOADS.values()}
+    kinds = {"recurrent_tc", "recurrent_tc_lstmp", "recurrent_simt", "recurrent_cluster",
+             "rssm_unroll", "bwd_recurrent"}
+    for (workload, kernel), traffic in bench.TRAFFIC.items():
+        assert workload in names, workload
+        assert kernel in kinds, kernel
+        assert traffic > 0
+
+
+def _chunk_starts(T, n):
+    # the chunked host pipeline's split: q steps, n-2 equal chunks, q steps
+    q = max(1, T // (4 * (n - 2) + 2)) if n >= 3 else 0
+    mid = n - 2 if n >= 3 else n
+    span = T - 2 * q
+    t = [0] + ([q] if q else []) + [q + span * i // mid for i in range(1, mid + 1)]
+    return t + ([T] if q else [])
+
+
+def test_host_chunk_boundaries_cover_every_step_once():
+    for T in range(1, 300):
+        for n in range(2, 17):
+            if n > T:
+                continue
+            t = _chunk_starts(T, n)
+            steps = [b - a for a, b in zip(t, t[1:])]
+            assert t[0] == 0 and t[-1] == T and min(steps) >= 1 and len(steps) <= 16
+    assert _chunk_starts(512, 8) == [0, 19, 98, 177, 256, 335, 414, 493, 512]
