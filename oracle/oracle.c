@@ -483,14 +483,16 @@ int oracle_num_threads_default(void) {
 
 /* ---------------------------------------------------------------------- */
 /* Backward pass through time (BPTT) of the stacked unidirectional          */
-/* LSTM / GRU without projection, lengths or clipping: the training use of  */
-/* the unrolled cell behind the RSSM page's Motivation and the LSTMP page's */
-/* training discussion.  The gradient of a scalar loss whose derivative     */
-/* with respect to y is dy [T,B,H] (and to h_n / c_n is dh_n / dc_n         */
-/* [L,B,H], NULL = 0) is taken through the forward recurrence exactly as    */
-/* written above, in reverse time, by the chain rule:                       */
-/*   LSTM  h = o tanh(c),  c = f c' + i g:                                  */
-/*     do = dh tanh(c);  dc += dh o (1 - tanh^2 c);                        */
+/* LSTM / GRU, optionally LSTM with projection, without lengths or          */
+/* clipping: the training use of the unrolled cell behind the RSSM page's   */
+/* Motivation and the LSTMP page's training discussion.  The gradient of a  */
+/* scalar loss whose derivative with respect to y is dy [T,B,Ho] (and to    */
+/* h_n / c_n is dh_n [L,B,Ho] / dc_n [L,B,H], NULL = 0; Ho = proj or H) is  */
+/* taken through the forward recurrence exactly as written above, in       */
+/* reverse time, by the chain rule:                                         */
+/*   LSTM  m = o tanh(c),  c = f c' + i g,  h = W_hr m (projection) or m:    */
+/*     dm = W_hr^T dh (projection; dW_hr += dh m^T) or dh;                  */
+/*     do = dm tanh(c);  dc += dm o (1 - tanh^2 c);                         */
 /*     di = dc g;  df = dc c';  dg = dc i;  dc' = dc f;                     */
 /*     dz = [di i(1-i), df f(1-f), dg (1-g^2), do o(1-o)]  (pre-activations)*/
 /*     dx_t = W_ih^T dz;  dh' = W_hh^T dz;  dW_ih += dz x^T;               */
@@ -504,38 +506,45 @@ int oracle_num_threads_default(void) {
 /*     dW_hh += dR h'^T;  db_ih += dA;  db_hh += dR                          */
 /* Layer l's dx is layer l-1's dy.  Weight gradients are summed over rows   */
 /* and steps; layouts follow the weights (layer l of dW_ih at offset        */
-/* sum_{j<l} nG*H*in_j, dW_hh at l*nG*H*H, db at l*nG*H).                    */
-/* Outputs: dx [T,B,in], dh0 [L,B,H], dc0 [L,B,H] (LSTM; may be NULL).      */
-int oracle_rnn_backward(int cell, int layers, int in_dim, int hidden, int T, int B,
+/* sum_{j<l} nG*H*in_j, dW_hh at l*nG*H*Ho, db at l*nG*H, dW_hr at l*P*H).  */
+/* Outputs: dx [T,B,in], dh0 [L,B,Ho], dc0 [L,B,H] (LSTM; may be NULL).     */
+int oracle_rnn_backward(int cell, int layers, int in_dim, int hidden, int proj, int T, int B,
                         const float *x, const float *h0, const float *c0,
                         const oracle_layer_w *w, const float *dy, const float *dh_n,
                         const float *dc_n, double *dx, double *dh0, double *dc0, double *dW_ih,
-                        double *dW_hh, double *db_ih, double *db_hh, int nthreads) {
+                        double *dW_hh, double *db_ih, double *db_hh, double *dW_hr,
+                        int nthreads) {
     if (cell != OR_LSTM && cell != OR_GRU) return -1;
     if (layers < 1 || in_dim < 1 || hidden < 1 || T < 1 || B < 1 || !x || !dy) return -1;
-    const int H = hidden, nG = (cell == OR_LSTM) ? 4 : 3, G = nG * H;
+    if (proj < 0 || (proj > 0 && cell != OR_LSTM)) return -1;
+    const int H = hidden, P = proj, Ho = proj > 0 ? proj : hidden;
+    const int nG = (cell == OR_LSTM) ? 4 : 3, G = nG * H;
     const int lstm = cell == OR_LSTM;
     size_t *off_ih = (size_t *)calloc((size_t)layers + 1, sizeof(size_t));
     double **Wih = (double **)calloc(layers, sizeof(double *));
     double **Whh = (double **)calloc(layers, sizeof(double *));
     double **bih = (double **)calloc(layers, sizeof(double *));
     double **bhh = (double **)calloc(layers, sizeof(double *));
+    double **Whr = (double **)calloc(layers, sizeof(double *));
     for (int l = 0; l < layers; ++l) {
-        const int in_w = l == 0 ? in_dim : H;
+        const int in_w = l == 0 ? in_dim : Ho;
         off_ih[l + 1] = off_ih[l] + (size_t)G * in_w;
         Wih[l] = widen(w[l].w_ih, (size_t)G * in_w, 0);
-        Whh[l] = widen(w[l].w_hh, (size_t)G * H, 0);
+        Whh[l] = widen(w[l].w_hh, (size_t)G * Ho, 0);
         bih[l] = widen(w[l].b_ih, (size_t)G, 0);
         bhh[l] = widen(w[l].b_hh, (size_t)G, 0);
+        Whr[l] = P > 0 ? widen(w[l].w_hr, (size_t)P * H, 0) : NULL;
     }
-    const int wmax = in_dim > H ? in_dim : H;
+    const int wmax = in_dim > Ho ? in_dim : Ho;
     int nth = 1;
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
     nth = omp_get_max_threads();
 #endif
     /* per-thread weight-gradient accumulators, summed in thread order at the end */
-    const size_t nw = off_ih[layers] + (size_t)layers * G * H + 2 * (size_t)layers * G;
+    const size_t n_ih = off_ih[layers], n_hh = (size_t)layers * G * Ho, n_b = (size_t)layers * G,
+                 n_hr = (size_t)layers * P * H;
+    const size_t nw = n_ih + n_hh + 2 * n_b + n_hr;
     double *acc = (double *)calloc((size_t)nth * nw, sizeof(double));
 #ifdef _OPENMP
 #pragma omp parallel
@@ -546,19 +555,22 @@ int oracle_rnn_backward(int cell, int layers, int in_dim, int hidden, int T, int
         tid = omp_get_thread_num();
 #endif
         double *gWih = acc + (size_t)tid * nw;
-        double *gWhh = gWih + off_ih[layers];
-        double *gbih = gWhh + (size_t)layers * G * H;
-        double *gbhh = gbih + (size_t)layers * G;
-        /* per row: every layer's input sequence, h_t (t = -1 .. T-1), c_t, gates */
+        double *gWhh = gWih + n_ih;
+        double *gbih = gWhh + n_hh;
+        double *gbhh = gbih + n_b;
+        double *gWhr = gbhh + n_b;
+        /* per row: every layer's input sequence, h_t (t = -1 .. T-1), c_t, m_t, gates */
         double *X = (double *)malloc((size_t)layers * T * wmax * sizeof(double));
-        double *hs = (double *)malloc((size_t)layers * (T + 1) * H * sizeof(double));
+        double *hs = (double *)malloc((size_t)layers * (T + 1) * Ho * sizeof(double));
         double *cs = (double *)malloc((size_t)layers * (T + 1) * H * sizeof(double));
+        double *ms = (double *)malloc((size_t)layers * T * H * sizeof(double));
         double *gt = (double *)malloc((size_t)layers * T * (G + H) * sizeof(double));
         double *dX = (double *)malloc((size_t)T * wmax * sizeof(double));
-        double *dY = (double *)malloc((size_t)T * H * sizeof(double));
-        double *dh = (double *)malloc((size_t)H * sizeof(double));
+        double *dY = (double *)malloc((size_t)T * Ho * sizeof(double));
+        double *dh = (double *)malloc((size_t)Ho * sizeof(double));
+        double *dm = (double *)malloc((size_t)H * sizeof(double));
         double *dc = (double *)malloc((size_t)H * sizeof(double));
-        double *dhp = (double *)malloc((size_t)H * sizeof(double));
+        double *dhp = (double *)malloc((size_t)Ho * sizeof(double));
         double *dA = (double *)malloc((size_t)G * sizeof(double));
         double *dR = (double *)malloc((size_t)G * sizeof(double));
         double *pre = (double *)malloc((size_t)2 * G * sizeof(double));
@@ -571,22 +583,23 @@ int oracle_rnn_backward(int cell, int layers, int in_dim, int hidden, int T, int
                 for (int k = 0; k < in_dim; ++k)
                     X[(size_t)t * wmax + k] = (double)x[((size_t)t * B + b) * in_dim + k];
             for (int l = 0; l < layers; ++l) {
-                const int in_w = l == 0 ? in_dim : H;
+                const int in_w = l == 0 ? in_dim : Ho;
                 const double *Xl = X + (size_t)l * T * wmax;
-                double *hl = hs + (size_t)l * (T + 1) * H, *cl = cs + (size_t)l * (T + 1) * H;
+                double *hl = hs + (size_t)l * (T + 1) * Ho, *cl = cs + (size_t)l * (T + 1) * H;
+                double *ml = ms + (size_t)l * T * H;
                 double *gl = gt + (size_t)l * T * (G + H);
-                for (int k = 0; k < H; ++k) {
-                    hl[k] = h0 ? (double)h0[((size_t)l * B + b) * H + k] : 0.0;
+                for (int k = 0; k < Ho; ++k) hl[k] = h0 ? (double)h0[((size_t)l * B + b) * Ho + k] : 0.0;
+                for (int k = 0; k < H; ++k)
                     cl[k] = (lstm && c0) ? (double)c0[((size_t)l * B + b) * H + k] : 0.0;
-                }
                 for (int t = 0; t < T; ++t) {
-                    const double *xt = Xl + (size_t)t * wmax, *hp = hl + (size_t)t * H;
-                    double *hn_ = hl + (size_t)(t + 1) * H, *cn_ = cl + (size_t)(t + 1) * H;
+                    const double *xt = Xl + (size_t)t * wmax, *hp = hl + (size_t)t * Ho;
+                    double *hn_ = hl + (size_t)(t + 1) * Ho, *cn_ = cl + (size_t)(t + 1) * H;
+                    double *mt = ml + (size_t)t * H;
                     double *g = gl + (size_t)t * (G + H);
                     for (int n = 0; n < G; ++n) {
                         double a = bih[l][n], r = bhh[l][n];
                         for (int k = 0; k < in_w; ++k) a += Wih[l][(size_t)n * in_w + k] * xt[k];
-                        for (int k = 0; k < H; ++k) r += Whh[l][(size_t)n * H + k] * hp[k];
+                        for (int k = 0; k < Ho; ++k) r += Whh[l][(size_t)n * Ho + k] * hp[k];
                         pre[n] = a;
                         pre[G + n] = r;
                     }
@@ -597,55 +610,77 @@ int oracle_rnn_backward(int cell, int layers, int in_dim, int hidden, int T, int
                             const double gg = tanh(pre[2 * H + u] + pre[G + 2 * H + u]);
                             const double o = sigmoid(pre[3 * H + u] + pre[G + 3 * H + u]);
                             cn_[u] = f * cl[(size_t)t * H + u] + i * gg;
-                            hn_[u] = o * tanh(cn_[u]);
+                            mt[u] = o * tanh(cn_[u]);
                             g[u] = i; g[H + u] = f; g[2 * H + u] = gg; g[3 * H + u] = o;
                         } else {
                             const double r = sigmoid(pre[u] + pre[G + u]);
                             const double z = sigmoid(pre[H + u] + pre[G + H + u]);
                             const double hnp = pre[G + 2 * H + u];  /* W_hn h' + b_hn */
                             const double n = tanh(pre[2 * H + u] + r * hnp);
-                            hn_[u] = (1.0 - z) * n + z * hp[u];
+                            mt[u] = (1.0 - z) * n + z * hp[u];
                             cn_[u] = 0.0;
                             g[u] = r; g[H + u] = z; g[2 * H + u] = n; g[G + u] = hnp;
                         }
                     }
+                    if (P > 0) {
+                        for (int q = 0; q < P; ++q) {
+                            double s2 = 0.0;
+                            for (int k = 0; k < H; ++k) s2 += Whr[l][(size_t)q * H + k] * mt[k];
+                            hn_[q] = s2;
+                        }
+                    } else {
+                        memcpy(hn_, mt, (size_t)H * sizeof(double));
+                    }
                     if (l + 1 < layers)
-                        memcpy(X + ((size_t)(l + 1) * T + t) * wmax, hn_, (size_t)H * sizeof(double));
+                        memcpy(X + ((size_t)(l + 1) * T + t) * wmax, hn_, (size_t)Ho * sizeof(double));
                 }
             }
             /* ---- backward, top layer first */
             for (int t = 0; t < T; ++t)
-                for (int k = 0; k < H; ++k) dY[(size_t)t * H + k] = (double)dy[((size_t)t * B + b) * H + k];
+                for (int k = 0; k < Ho; ++k) dY[(size_t)t * Ho + k] = (double)dy[((size_t)t * B + b) * Ho + k];
             for (int l = layers - 1; l >= 0; --l) {
-                const int in_w = l == 0 ? in_dim : H;
+                const int in_w = l == 0 ? in_dim : Ho;
                 const double *Xl = X + (size_t)l * T * wmax;
-                const double *hl = hs + (size_t)l * (T + 1) * H, *cl = cs + (size_t)l * (T + 1) * H;
+                const double *hl = hs + (size_t)l * (T + 1) * Ho, *cl = cs + (size_t)l * (T + 1) * H;
+                const double *ml = ms + (size_t)l * T * H;
                 const double *gl = gt + (size_t)l * T * (G + H);
-                for (int k = 0; k < H; ++k) {
-                    dhp[k] = dh_n ? (double)dh_n[((size_t)l * B + b) * H + k] : 0.0;
+                for (int k = 0; k < Ho; ++k) dhp[k] = dh_n ? (double)dh_n[((size_t)l * B + b) * Ho + k] : 0.0;
+                for (int k = 0; k < H; ++k)
                     dc[k] = (lstm && dc_n) ? (double)dc_n[((size_t)l * B + b) * H + k] : 0.0;
-                }
                 for (int t = T - 1; t >= 0; --t) {
                     const double *g = gl + (size_t)t * (G + H);
-                    const double *hp = hl + (size_t)t * H, *xt = Xl + (size_t)t * wmax;
-                    for (int u = 0; u < H; ++u) dh[u] = dY[(size_t)t * H + u] + dhp[u];
+                    const double *hp = hl + (size_t)t * Ho, *xt = Xl + (size_t)t * wmax;
+                    const double *mt = ml + (size_t)t * H;
+                    for (int q = 0; q < Ho; ++q) dh[q] = dY[(size_t)t * Ho + q] + dhp[q];
+                    if (P > 0) {
+                        double *gWr = gWhr + (size_t)l * P * H;
+                        for (int k = 0; k < H; ++k) {
+                            double s2 = 0.0;
+                            for (int q = 0; q < P; ++q) s2 += Whr[l][(size_t)q * H + k] * dh[q];
+                            dm[k] = s2;
+                        }
+                        for (int q = 0; q < P; ++q)
+                            for (int k = 0; k < H; ++k) gWr[(size_t)q * H + k] += dh[q] * mt[k];
+                    } else {
+                        memcpy(dm, dh, (size_t)H * sizeof(double));
+                    }
                     for (int u = 0; u < H; ++u) {
                         if (lstm) {
                             const double i = g[u], f = g[H + u], gg = g[2 * H + u], o = g[3 * H + u];
                             const double c = cl[(size_t)(t + 1) * H + u], cp = cl[(size_t)t * H + u];
                             const double tc = tanh(c);
-                            const double dcu = dc[u] + dh[u] * o * (1.0 - tc * tc);
+                            const double dcu = dc[u] + dm[u] * o * (1.0 - tc * tc);
                             dA[u] = dcu * gg * i * (1.0 - i);
                             dA[H + u] = dcu * cp * f * (1.0 - f);
                             dA[2 * H + u] = dcu * i * (1.0 - gg * gg);
-                            dA[3 * H + u] = dh[u] * tc * o * (1.0 - o);
+                            dA[3 * H + u] = dm[u] * tc * o * (1.0 - o);
                             dc[u] = dcu * f;
                             dR[u] = dA[u]; dR[H + u] = dA[H + u];
                             dR[2 * H + u] = dA[2 * H + u]; dR[3 * H + u] = dA[3 * H + u];
                         } else {
                             const double r = g[u], z = g[H + u], n = g[2 * H + u], hnp = g[G + u];
-                            const double dn = dh[u] * (1.0 - z);
-                            const double dz = dh[u] * (hp[u] - n);
+                            const double dn = dm[u] * (1.0 - z);
+                            const double dz = dm[u] * (hp[u] - n);
                             const double dan = dn * (1.0 - n * n);
                             const double dr = dan * hnp;
                             dA[u] = dr * r * (1.0 - r);
@@ -656,31 +691,31 @@ int oracle_rnn_backward(int cell, int layers, int in_dim, int hidden, int T, int
                         }
                     }
                     /* gradients of this step's weights, input and previous state */
-                    double *gWi = gWih + off_ih[l], *gWh = gWhh + (size_t)l * G * H;
+                    double *gWi = gWih + off_ih[l], *gWh = gWhh + (size_t)l * G * Ho;
                     for (int n = 0; n < G; ++n) {
                         for (int k = 0; k < in_w; ++k) gWi[(size_t)n * in_w + k] += dA[n] * xt[k];
-                        for (int k = 0; k < H; ++k) gWh[(size_t)n * H + k] += dR[n] * hp[k];
+                        for (int k = 0; k < Ho; ++k) gWh[(size_t)n * Ho + k] += dR[n] * hp[k];
                         gbih[(size_t)l * G + n] += dA[n];
                         gbhh[(size_t)l * G + n] += dR[n];
                     }
                     for (int k = 0; k < in_w; ++k) {
-                        double s = 0.0;
-                        for (int n = 0; n < G; ++n) s += Wih[l][(size_t)n * in_w + k] * dA[n];
-                        dX[(size_t)t * wmax + k] = s;
+                        double s2 = 0.0;
+                        for (int n = 0; n < G; ++n) s2 += Wih[l][(size_t)n * in_w + k] * dA[n];
+                        dX[(size_t)t * wmax + k] = s2;
                     }
-                    for (int k = 0; k < H; ++k) {
-                        double s = lstm ? 0.0 : dh[k] * g[H + k];  /* GRU: direct path z h' */
-                        for (int n = 0; n < G; ++n) s += Whh[l][(size_t)n * H + k] * dR[n];
-                        dhp[k] = s;
+                    for (int k = 0; k < Ho; ++k) {
+                        double s2 = lstm ? 0.0 : dm[k] * g[H + k];  /* GRU: direct path z h' */
+                        for (int n = 0; n < G; ++n) s2 += Whh[l][(size_t)n * Ho + k] * dR[n];
+                        dhp[k] = s2;
                     }
                 }
-                for (int k = 0; k < H; ++k) {
-                    if (dh0) dh0[((size_t)l * B + b) * H + k] = dhp[k];
+                for (int k = 0; k < Ho; ++k)
+                    if (dh0) dh0[((size_t)l * B + b) * Ho + k] = dhp[k];
+                for (int k = 0; k < H; ++k)
                     if (dc0 && lstm) dc0[((size_t)l * B + b) * H + k] = dc[k];
-                }
                 if (l > 0) {
                     for (int t = 0; t < T; ++t)
-                        memcpy(dY + (size_t)t * H, dX + (size_t)t * wmax, (size_t)H * sizeof(double));
+                        memcpy(dY + (size_t)t * Ho, dX + (size_t)t * wmax, (size_t)Ho * sizeof(double));
                 } else if (dx) {
                     for (int t = 0; t < T; ++t)
                         for (int k = 0; k < in_dim; ++k)
@@ -688,25 +723,26 @@ int oracle_rnn_backward(int cell, int layers, int in_dim, int hidden, int T, int
                 }
             }
         }
-        free(X); free(hs); free(cs); free(gt); free(dX); free(dY);
-        free(dh); free(dc); free(dhp); free(dA); free(dR); free(pre);
+        free(X); free(hs); free(cs); free(ms); free(gt); free(dX); free(dY);
+        free(dh); free(dm); free(dc); free(dhp); free(dA); free(dR); free(pre);
     }
     /* sum the per-thread accumulators in thread order */
-    double *outs[4] = {dW_ih, dW_hh, db_ih, db_hh};
-    const size_t lens[4] = {off_ih[layers], (size_t)layers * G * H, (size_t)layers * G,
-                            (size_t)layers * G};
+    double *outs[5] = {dW_ih, dW_hh, db_ih, db_hh, dW_hr};
+    const size_t lens[5] = {n_ih, n_hh, n_b, n_b, n_hr};
     size_t base = 0;
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 5; ++j) {
         if (outs[j])
             for (size_t e = 0; e < lens[j]; ++e) {
-                double s = 0.0;
-                for (int q = 0; q < nth; ++q) s += acc[(size_t)q * nw + base + e];
-                outs[j][e] = s;
+                double s2 = 0.0;
+                for (int q = 0; q < nth; ++q) s2 += acc[(size_t)q * nw + base + e];
+                outs[j][e] = s2;
             }
         base += lens[j];
     }
     free(acc);
-    for (int l = 0; l < layers; ++l) { free(Wih[l]); free(Whh[l]); free(bih[l]); free(bhh[l]); }
-    free(Wih); free(Whh); free(bih); free(bhh); free(off_ih);
+    for (int l = 0; l < layers; ++l) {
+        free(Wih[l]); free(Whh[l]); free(bih[l]); free(bhh[l]); free(Whr[l]);
+    }
+    free(Wih); free(Whh); free(bih); free(bhh); free(Whr); free(off_ih);
     return 0;
 }

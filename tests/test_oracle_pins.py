@@ -775,3 +775,77 @@ def test_bptt_finite_differences(cell):
                 w2[layer][k] = a
                 return x, w2, h0, c0
             check(ws[layer][k], g[gk][layer], rebuild)
+
+
+@pytest.mark.parametrize("layers", [1, 2])
+def test_bptt_projection_against_torch_autograd(layers):
+    """LSTM with projection: the oracle's gradients (dw_hr included) equal
+    torch float64 autograd through nn.LSTM(proj_size=P)."""
+    rng = np.random.default_rng(40 + layers)
+    T, B, in_dim, H, P = 5, 3, 4, 6, 3
+    ws = _rand_weights(rng, oracle.LSTM, layers, in_dim, H, proj=P)
+    x = rng.standard_normal((T, B, in_dim)).astype(np.float32)
+    h0 = (0.5 * rng.standard_normal((layers, B, P))).astype(np.float32)
+    c0 = (0.5 * rng.standard_normal((layers, B, H))).astype(np.float32)
+    dy = rng.standard_normal((T, B, P)).astype(np.float32)
+    dhn = rng.standard_normal((layers, B, P)).astype(np.float32)
+    dcn = rng.standard_normal((layers, B, H)).astype(np.float32)
+    g = oracle.rnn_backward(oracle.LSTM, x, ws, dy, hidden=H, proj=P, h0=h0, c0=c0, dh_n=dhn,
+                            dc_n=dcn)
+    mod = torch.nn.LSTM(input_size=in_dim, hidden_size=H, num_layers=layers, proj_size=P,
+                        dtype=torch.float64)
+    names = (("w_ih", "weight_ih"), ("w_hh", "weight_hh"), ("b_ih", "bias_ih"),
+             ("b_hh", "bias_hh"), ("w_hr", "weight_hr"))
+    with torch.no_grad():
+        for layer in range(layers):
+            for k, name in names:
+                getattr(mod, f"{name}_l{layer}").copy_(torch.from_numpy(ws[layer][k]).double())
+    xt = torch.from_numpy(x).double().requires_grad_()
+    ht = torch.from_numpy(h0).double().requires_grad_()
+    ct = torch.from_numpy(c0).double().requires_grad_()
+    y, (hn, cn) = mod(xt, (ht, ct))
+    loss = (y * torch.from_numpy(dy).double()).sum() + (hn * torch.from_numpy(dhn).double()).sum() \
+        + (cn * torch.from_numpy(dcn).double()).sum()
+    loss.backward()
+    tol = dict(rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(g["dx"], xt.grad.numpy(), **tol)
+    np.testing.assert_allclose(g["dh0"], ht.grad.numpy(), **tol)
+    np.testing.assert_allclose(g["dc0"], ct.grad.numpy(), **tol)
+    for layer in range(layers):
+        for k, name in names:
+            np.testing.assert_allclose(g["d" + k][layer],
+                                       getattr(mod, f"{name}_l{layer}").grad.numpy(), **tol,
+                                       err_msg=f"d{k} layer {layer}")
+
+
+def test_bptt_projection_finite_differences():
+    rng = np.random.default_rng(55)
+    T, B, in_dim, H, P, layers = 4, 2, 3, 5, 2, 2
+    ws = _rand_weights(rng, oracle.LSTM, layers, in_dim, H, proj=P)
+    x = rng.standard_normal((T, B, in_dim)).astype(np.float32)
+    h0 = (0.5 * rng.standard_normal((layers, B, P))).astype(np.float32)
+    c0 = (0.5 * rng.standard_normal((layers, B, H))).astype(np.float32)
+    dy = rng.standard_normal((T, B, P)).astype(np.float32)
+    dhn = rng.standard_normal((layers, B, P)).astype(np.float32)
+
+    def loss(ws_):
+        y, hn, _ = oracle.rnn_forward(oracle.LSTM, x, ws_, hidden=H, proj=P, h0=h0, c0=c0)
+        return float((y * dy).sum() + (hn * dhn).sum())
+
+    g = oracle.rnn_backward(oracle.LSTM, x, ws, dy, hidden=H, proj=P, h0=h0, c0=c0, dh_n=dhn)
+    eps = np.float32(2.0 ** -10)
+    for layer in range(layers):
+        for k, gk in (("w_hr", "dw_hr"), ("w_hh", "dw_hh"), ("w_ih", "dw_ih")):
+            arr = ws[layer][k]
+            for idx in ((0, 0), (arr.shape[0] - 1, arr.shape[1] - 1)):
+                hi, lo = arr.copy(), arr.copy()
+                hi[idx] += eps
+                lo[idx] -= eps
+                w_hi = [dict(w) for w in ws]
+                w_lo = [dict(w) for w in ws]
+                w_hi[layer][k] = hi
+                w_lo[layer][k] = lo
+                fd = (loss(w_hi) - loss(w_lo)) / (2 * float(eps))
+                want = g[gk][layer][idx]
+                assert abs(fd - want) <= 1e-5 * max(1.0, abs(want)), (layer, k, idx, fd, want)
+
