@@ -97,7 +97,7 @@ def load(path: Optional[str] = None):
             "rssm_unroll_actor": (I, [P, I, I] + [P] * 8 + [P]),
             "rnn_forward_host": (I, [P, I, I] + [P] * 8),
             "rnn_backward": (I, [P, I, I] + [P] * 10),
-            "rnn_get_weight_grads": (I, [P, I, I, P, P, P, P, P]),
+            "rnn_get_weight_grads": (I, [P, I, I, P, P, P, P, P, P]),
             "rssm_unroll_host": (I, [P, I, I] + [P] * 8 + [P]),
             "rssm_unroll_actor_host": (I, [P, I, I] + [P] * 8 + [P]),
         }
@@ -268,8 +268,8 @@ def rnn_backward(h, T: int, B: int, x, h0, c0, dy, dh_n, dc_n, dx, dh0, dc0, str
                                _stream(stream)))
 
 
-def rnn_get_weight_grads(h, layer: int, dW_ih, dW_hh, db_ih, db_hh, stream=None):
-    outs = [_dev(t) for t in (dW_ih, dW_hh, db_ih, db_hh)]
+def rnn_get_weight_grads(h, layer: int, dW_ih, dW_hh, db_ih, db_hh, dW_hr=None, stream=None):
+    outs = [_dev(t) for t in (dW_ih, dW_hh, db_ih, db_hh, dW_hr)]
     _check(load().rnn_get_weight_grads(h, layer, 0, *[k[1] for k in outs], _stream(stream)))
 
 
@@ -389,18 +389,21 @@ class RNN:
         T, B, in_dim = x.shape
         dev = x.device
         dx = torch.empty_like(x)
-        dh0 = torch.empty((self.layers, B, self.hidden), device=dev)
-        dc0 = torch.empty_like(dh0) if self.cell == "lstm" else None
+        dh0 = torch.empty((self.layers, B, self.Hout), device=dev)
+        dc0 = torch.empty((self.layers, B, self.hidden), device=dev) \
+            if self.cell == "lstm" else None
         rnn_backward(self.h, T, B, x, h0, c0, dy, dh_n, dc_n, dx, dh0, dc0, stream)
         nG = 4 if self.cell == "lstm" else 3
         grads = []
         for layer in range(self.layers):
-            k = in_dim if layer == 0 else self.hidden
+            k = in_dim if layer == 0 else self.Hout
             g = {"w_ih": torch.empty((nG * self.hidden, k), device=dev),
-                 "w_hh": torch.empty((nG * self.hidden, self.hidden), device=dev),
+                 "w_hh": torch.empty((nG * self.hidden, self.Hout), device=dev),
                  "b_ih": torch.empty((nG * self.hidden,), device=dev),
-                 "b_hh": torch.empty((nG * self.hidden,), device=dev)}
-            rnn_get_weight_grads(self.h, layer, g["w_ih"], g["w_hh"], g["b_ih"], g["b_hh"], stream)
+                 "b_hh": torch.empty((nG * self.hidden,), device=dev),
+                 "w_hr": torch.empty((self.proj, self.hidden), device=dev) if self.proj else None}
+            rnn_get_weight_grads(self.h, layer, g["w_ih"], g["w_hh"], g["b_ih"], g["b_hh"],
+                                 g["w_hr"], stream)
             grads.append(g)
         return dx, dh0, dc0, grads
 

@@ -169,9 +169,9 @@ struct LayerDirW {
   // bf16 LSTMP tensor-core path: packed W_hh W_hr, fp32 copy of the rounded
   // W_hh (initial-state term) and bf16 W_hr [P][round_up(H, 8)] (projection GEMM)
   DevBuf fold_w, whh_f32, whr_bf;
-  // fp32 handles without projection: plain W_hh [nG*H][round_up(H, 8)], b_ih,
-  // b_hh (zeros when NULL) for the backward pass
-  DevBuf whh_plain, bih_plain, bhh_plain;
+  // fp32 handles, for the backward pass: plain W_hh [nG*H][round_up(Hout, 8)],
+  // b_ih, b_hh (zeros when NULL), and W_hr [P][H] with a projection
+  DevBuf whh_plain, bih_plain, bhh_plain, whr_plain;
   bool set = false;
 };
 
@@ -539,14 +539,15 @@ extern "C" int rnn_set_weights(rcu_rnn_t h, int layer, int dir, const float *W_i
     CU(lw.whr_bf.upload(hr.data(), hr.size() * 2));
   }
   // --- plain fp32 copies for the backward pass
-  if (!bf && P == 0) {
-    const int ldh = round_up(H, 8);
-    std::vector<float> wp((size_t)nG * H * ldh, 0.f);
+  if (!bf) {
+    const int ldo = round_up(Hout, 8);
+    std::vector<float> wp((size_t)nG * H * ldo, 0.f);
     for (int r = 0; r < nG * H; ++r)
-      for (int k = 0; k < H; ++k) wp[(size_t)r * ldh + k] = whh[(size_t)r * Hout + k];
+      for (int k = 0; k < Hout; ++k) wp[(size_t)r * ldo + k] = whh[(size_t)r * Hout + k];
     CU(lw.whh_plain.upload(wp.data(), wp.size() * 4));
     CU(lw.bih_plain.upload(bih.data(), (size_t)nG * H * 4));
     CU(lw.bhh_plain.upload(bhh.data(), (size_t)nG * H * 4));
+    if (P > 0) CU(lw.whr_plain.upload(whr.data(), (size_t)P * H * 4));
   }
   lw.set = true;
   return RCU_OK;
@@ -1000,12 +1001,18 @@ extern "C" int rnn_forward_host(rcu_rnn_t h, int T, int B, const float *x, const
   return RCU_OK;
 }
 
-// Backward pass through time (fp32 handles, unidirectional, no projection,
-// lengths or clipping).  Recompute design: the forward is run again keeping
-// every layer's output, which makes all of h_{t-1} known, so the layer's
-// pre-activations are two GEMMs over all steps and the LSTM cell sequence one
-// elementwise scan; only dh_{t-1} = W_hh^T dR_t runs step by step
-// (bwd_rec_kernel).  Weight and input gradients are GEMMs over all T*B rows.
+// Backward pass through time (fp32 handles, unidirectional, no lengths or
+// clipping; LSTM optionally with projection).  Recompute design: the forward
+// is run again keeping every layer's output, which makes all of h_{t-1}
+// known, so the layer's pre-activations are two GEMMs over all steps and the
+// LSTM cell sequence one elementwise scan; only the hidden-state gradient
+// runs step by step (bwd_rec_kernel).  Weight and input gradients are GEMMs
+// over all T*B rows.
+// With a projection h = W_hr m the step recurrence is
+//   dh_t = dy_t + W_hh^T dz_{t+1} (width P),  dm_t = W_hr^T dh_t (width H),
+// so dm_t = W_hr^T dy_t + (W_hh W_hr)^T dz_{t+1}: the same kernel runs it with
+// W_hh W_hr in place of W_hh and A = dy W_hr (one GEMM, dh_n folded into the
+// last step) in place of dy; dh_t, dh0 and dW_hr follow from GEMMs.
 extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const float *h0,
                             const float *c0, const float *dy, const float *dh_n,
                             const float *dc_n, float *dx, float *dh0, float *dc0, void *stream) {
@@ -1013,32 +1020,37 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
   h->launches = 0;
   for (auto &w : h->lw)
     if (!w.set) return fail(RCU_ERR_STATE, "rnn_backward: weights missing for some layer/direction");
-  if (h->dtype != RCU_F32 || h->D != 1 || h->P != 0 || h->cclip || h->pclip)
-    return fail(RCU_ERR_UNSUPPORTED,
-                "rnn_backward: fp32 unidirectional networks without projection or clipping");
+  if (h->dtype != RCU_F32 || h->D != 1 || h->cclip || h->pclip)
+    return fail(RCU_ERR_UNSUPPORTED, "rnn_backward: fp32 unidirectional networks without clipping");
   if (T < 1 || B < 1 || !x || !dy) return fail(RCU_ERR_INVALID, "rnn_backward: need T, B >= 1, x and dy");
   if (h->cell == RCU_GRU && (c0 || dc_n || dc0))
     return fail(RCU_ERR_INVALID, "rnn_backward: c0/dc_n/dc0 are LSTM-only");
   if ((size_t)T * B > (size_t)INT32_MAX / 8)
     return fail(RCU_ERR_UNSUPPORTED, "rnn_backward: T*B too large");
   const int L = h->layers, H = h->H, nG = h->nG, G = nG * H, cell = h->cell;
+  const int P = h->P, Ho = h->Hout;
   if (bwd_units_per_cta(H, B, nG, h->nsm) < 1)
     return fail(RCU_ERR_UNSUPPORTED, "rnn_backward: W_hh columns do not fit one SM per unit group");
   cudaStream_t s = (cudaStream_t)stream;
   const int M = T * B;
-  const size_t TBH = (size_t)M * H, TBG = (size_t)M * G;
-  int kmax = H;
+  const size_t TBH = (size_t)M * H, TBO = (size_t)M * Ho, TBG = (size_t)M * G;
+  const int ldh = round_up(H, 8), ldo = round_up(Ho, 8);
+  int kmax = std::max(H, Ho);
   for (int l = 0; l < L; ++l) kmax = std::max(kmax, h->in_l[l]);
   // ---- workspace (floats; every piece 256-byte aligned)
   size_t off = 0;
   auto take = [&](size_t n) { size_t r = off; off += (n + 63) & ~size_t(63); return r; };
-  const size_t o_keep = take((size_t)L * TBH), o_hp = take(TBH), o_zin = take(TBG),
+  const size_t o_keep = take((size_t)L * TBO), o_hp = take(TBO), o_zin = take(TBG),
                o_zh = take(TBG), o_cs = take(cell == RCU_LSTM ? TBH : 0), o_da = take(TBG),
-               o_dr = take(cell == RCU_GRU ? TBG : 0), o_dya = take(TBH), o_dyb = take(TBH),
+               o_dr = take(cell == RCU_GRU ? TBG : 0), o_dya = take(TBO), o_dyb = take(TBO),
                o_t1 = take(TBG), o_t2 = take((size_t)M * kmax),
-               o_t3 = take(cell == RCU_GRU ? TBG : 0), o_t4 = take(TBH),
-               o_wt = take((size_t)kmax * G),
-               o_cs2 = take(colsum_scratch_floats(M, G)), o_ctl = take(64);
+               o_t3 = take(cell == RCU_GRU ? TBG : 0), o_t4 = take(TBO),
+               o_wt = take((size_t)kmax * G), o_cs2 = take(colsum_scratch_floats(M, G)),
+               // projection only
+               o_ms = take(P ? TBH : 0), o_dyp = take(P ? TBO : 0), o_a = take(P ? TBH : 0),
+               o_f = take(P ? (size_t)G * ldh : 0), o_whrt = take(P ? (size_t)H * P : 0),
+               o_whht = take(P ? (size_t)Ho * G : 0), o_r = take(P ? TBO : 0),
+               o_t5 = take(P ? TBH : 0), o_t6 = take(P ? TBO : 0), o_ctl = take(64);
   CU(h->bw.ensure(off * 4));
   float *wsf = (float *)h->bw.p;
   float *keep = wsf + o_keep, *hp = wsf + o_hp, *zin = wsf + o_zin, *zh = wsf + o_zh;
@@ -1047,13 +1059,16 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
   float *dYa = wsf + o_dya, *dYb = wsf + o_dyb, *T1 = wsf + o_t1, *T2 = wsf + o_t2;
   float *T3 = cell == RCU_GRU ? wsf + o_t3 : T1, *T4 = wsf + o_t4;
   float *WT = wsf + o_wt, *csum = wsf + o_cs2;
+  float *ms = P ? wsf + o_ms : nullptr, *dYp = wsf + o_dyp, *Aw = wsf + o_a, *Fw = wsf + o_f;
+  float *WhrT = wsf + o_whrt, *WhhT = wsf + o_whht, *Rw = wsf + o_r, *T5 = wsf + o_t5,
+        *T6 = wsf + o_t6;
   unsigned *ctr = (unsigned *)(wsf + o_ctl);
   if ((int)h->gw.size() < L) h->gw.resize(L);
   h->grads_ready = false;
   int launches = 0;
   // ---- forward again, keeping every layer's output sequence
   h->keep_out = keep;
-  int rc = rnn_forward(h, T, B, x, nullptr, h0, c0, nullptr, keep + (size_t)(L - 1) * TBH,
+  int rc = rnn_forward(h, T, B, x, nullptr, h0, c0, nullptr, keep + (size_t)(L - 1) * TBO,
                        nullptr, nullptr, stream);
   h->keep_out = nullptr;
   if (rc != RCU_OK) return rc;
@@ -1062,15 +1077,16 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
   int *err = (int *)h->ctl.p;
   const float *dYcur = dy;
   for (int l = L - 1; l >= 0; --l) {
-    const int K = h->in_l[l], ldk = round_up(K, 8), ldh = round_up(H, 8);
+    const int K = h->in_l[l], ldk = round_up(K, 8);
     const LayerDirW &lw = h->lw[(size_t)l];
-    const float *X = l == 0 ? x : keep + (size_t)(l - 1) * TBH;
+    const float *X = l == 0 ? x : keep + (size_t)(l - 1) * TBO;
     float *dX = l == 0 ? dx : (dYcur == dYa ? dYb : dYa);
+    const float *dhnl = dh_n ? dh_n + (size_t)l * B * Ho : nullptr;
     // h_{t-1} for t = 0 .. T-1
-    if (h0) CU(cudaMemcpyAsync(hp, h0 + (size_t)l * B * H, (size_t)B * H * 4, cudaMemcpyDeviceToDevice, s));
-    else CU(cudaMemsetAsync(hp, 0, (size_t)B * H * 4, s));
+    if (h0) CU(cudaMemcpyAsync(hp, h0 + (size_t)l * B * Ho, (size_t)B * Ho * 4, cudaMemcpyDeviceToDevice, s));
+    else CU(cudaMemsetAsync(hp, 0, (size_t)B * Ho * 4, s));
     if (T > 1)
-      CU(cudaMemcpyAsync(hp + (size_t)B * H, keep + (size_t)l * TBH, (size_t)(T - 1) * B * H * 4,
+      CU(cudaMemcpyAsync(hp + (size_t)B * Ho, keep + (size_t)l * TBO, (size_t)(T - 1) * B * Ho * 4,
                          cudaMemcpyDeviceToDevice, s));
     // pre-activations of every step
     h->begin("bwd_recompute_gemm", s);
@@ -1078,25 +1094,44 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
                                                    (const float *)lw.bih_plain.p, zin, G, M,
                                                    nullptr, G, K, s, err);
     if (e == cudaSuccess)
-      e = launch_gemm_simt<float, float>(hp, H, (const float *)lw.whh_plain.p, ldh,
-                                         (const float *)lw.bhh_plain.p, zh, G, M, nullptr, G, H,
+      e = launch_gemm_simt<float, float>(hp, Ho, (const float *)lw.whh_plain.p, ldo,
+                                         (const float *)lw.bhh_plain.p, zh, G, M, nullptr, G, Ho,
                                          s, err);
     h->end(s);
     const float *c0l = c0 ? c0 + (size_t)l * B * H : nullptr;
     h->begin("bwd_prep", s);
-    if (e == cudaSuccess) e = launch_bwd_prep(T, B, H, cell, zin, zh, c0l, cs, s);
+    if (e == cudaSuccess) e = launch_bwd_prep(T, B, H, cell, zin, zh, c0l, cs, ms, s);
     h->end(s);
     if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: recompute: %s", cudaGetErrorString(e));
+    // projection: dy' = dy (+ dh_n at the last step), A = dy' W_hr, F = W_hh W_hr
+    const float *rec_dy = dYcur, *rec_W = (const float *)lw.whh_plain.p;
+    int rec_ldw = ldo;
+    if (P > 0) {
+      h->begin("bwd_proj_fold", s);
+      CU(cudaMemcpyAsync(dYp, dYcur, TBO * 4, cudaMemcpyDeviceToDevice, s));
+      if (dhnl) e = launch_add(dYp + (size_t)(T - 1) * B * Ho, dhnl, (size_t)B * Ho, s);
+      if (e == cudaSuccess) e = launch_transpose((const float *)lw.whr_plain.p, P, H, H, WhrT, P, s);
+      if (e == cudaSuccess)
+        e = launch_gemm_simt<float, float>(dYp, Ho, WhrT, P, nullptr, Aw, H, M, nullptr, H, P, s, err);
+      if (e == cudaSuccess)
+        e = launch_gemm_simt<float, float>((const float *)lw.whh_plain.p, ldo, WhrT, P, nullptr, Fw,
+                                           ldh, G, nullptr, H, P, s, err);
+      h->end(s);
+      if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: projection: %s", cudaGetErrorString(e));
+      rec_dy = Aw;
+      rec_W = Fw;
+      rec_ldw = ldh;
+    }
     // the reverse-time recurrence
     CU(cudaMemsetAsync(ctr, 0, 16 * 4, s));
     BwdRecArgs a{};
     a.T = T; a.B = B; a.H = H; a.cell = cell;
-    a.Whh = (const float *)lw.whh_plain.p; a.ldw = ldh;
-    a.gates = zin; a.zh = zh; a.cs = cs; a.c0 = c0l; a.hp = hp; a.dy = dYcur;
-    a.dhn = dh_n ? dh_n + (size_t)l * B * H : nullptr;
+    a.Whh = rec_W; a.ldw = rec_ldw;
+    a.gates = zin; a.zh = zh; a.cs = cs; a.c0 = c0l; a.hp = hp; a.dy = rec_dy;
+    a.dhn = P > 0 ? nullptr : dhnl;
     a.dcn = dc_n ? dc_n + (size_t)l * B * H : nullptr;
     a.DA = DA; a.DR = DR;
-    a.dh0 = dh0 ? dh0 + (size_t)l * B * H : nullptr;
+    a.dh0 = (P > 0 || !dh0) ? nullptr : dh0 + (size_t)l * B * H;
     a.dc0 = dc0 ? dc0 + (size_t)l * B * H : nullptr;
     a.ctr = ctr; a.err = err; a.timeout_ns = (uint64_t)h->timeout_ns;
     a.drop_arrival = h->drop_arrival == 2 && l == L - 1;
@@ -1104,24 +1139,41 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
     e = launch_bwd_rec(a, h->nsm, s);
     h->end(s);
     if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: recurrence: %s", cudaGetErrorString(e));
+    DevBuf &g = h->gw[l];
+    CU(g.ensure(((size_t)G * K + (size_t)G * Ho + 2 * (size_t)G + (size_t)P * H) * 4));
+    float *gWih = (float *)g.p, *gWhh = gWih + (size_t)G * K, *gbih = gWhh + (size_t)G * Ho,
+          *gbhh = gbih + G, *gWhr = gbhh + G;
+    // projection: R = DZ W_hh (R_t = W_hh^T dz_t), dh0 = R_0, dh_t = dy'_t + R_{t+1},
+    // dW_hr = sum_t dh_t m_t^T
+    if (P > 0) {
+      h->begin("bwd_proj_grad", s);
+      e = launch_transpose((const float *)lw.whh_plain.p, G, Ho, ldo, WhhT, G, s);
+      if (e == cudaSuccess)
+        e = launch_gemm_simt<float, float>(DA, G, WhhT, G, nullptr, Rw, Ho, M, nullptr, Ho, G, s, err);
+      if (e == cudaSuccess && dh0)
+        e = cudaMemcpyAsync(dh0 + (size_t)l * B * Ho, Rw, (size_t)B * Ho * 4, cudaMemcpyDeviceToDevice, s);
+      if (e == cudaSuccess && T > 1) e = launch_add(dYp, Rw + (size_t)B * Ho, (size_t)(T - 1) * B * Ho, s);
+      if (e == cudaSuccess) e = launch_transpose(dYp, M, Ho, Ho, T6, M, s);
+      if (e == cudaSuccess) e = launch_transpose(ms, M, H, H, T5, M, s);
+      if (e == cudaSuccess)
+        e = launch_gemm_simt<float, float>(T6, M, T5, M, nullptr, gWhr, H, P, nullptr, H, M, s, err);
+      h->end(s);
+      if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: projection gradients: %s", cudaGetErrorString(e));
+    }
     // weight gradients: dW_ih = DA^T X, dW_hh = DR^T H_prev (through transposes
     // to K-contiguous operands), db = column sums; input gradient dX = DA W_ih
-    DevBuf &g = h->gw[l];
-    CU(g.ensure(((size_t)G * K + (size_t)G * H + 2 * (size_t)G) * 4));
-    float *gWih = (float *)g.p, *gWhh = gWih + (size_t)G * K, *gbih = gWhh + (size_t)G * H,
-          *gbhh = gbih + G;
     h->begin("bwd_transpose", s);
     e = launch_transpose(DA, M, G, G, T1, M, s);
     if (e == cudaSuccess) e = launch_transpose(X, M, K, K, T2, M, s);
     if (e == cudaSuccess && cell == RCU_GRU) e = launch_transpose(DR, M, G, G, T3, M, s);
-    if (e == cudaSuccess) e = launch_transpose(hp, M, H, H, T4, M, s);
+    if (e == cudaSuccess) e = launch_transpose(hp, M, Ho, Ho, T4, M, s);
     if (e == cudaSuccess) e = launch_transpose((const float *)h->wih[l].p, G, K, ldk, WT, G, s);
     h->end(s);
     h->begin("bwd_weight_gemm", s);
     if (e == cudaSuccess)
       e = launch_gemm_simt<float, float>(T1, M, T2, M, nullptr, gWih, K, G, nullptr, K, M, s, err);
     if (e == cudaSuccess)
-      e = launch_gemm_simt<float, float>(T3, M, T4, M, nullptr, gWhh, H, G, nullptr, H, M, s, err);
+      e = launch_gemm_simt<float, float>(T3, M, T4, M, nullptr, gWhh, Ho, G, nullptr, Ho, M, s, err);
     h->end(s);
     h->begin("bwd_colsum", s);
     if (e == cudaSuccess) e = launch_colsum(DA, M, G, csum, gbih, s);
@@ -1132,8 +1184,9 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
       e = launch_gemm_simt<float, float>(DA, G, WT, G, nullptr, dX, K, M, nullptr, K, G, s, err);
     h->end(s);
     if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: gradients: %s", cudaGetErrorString(e));
-    // 5 GEMMs, 4 or 5 transposes, prep, recurrence, 2 two-kernel column sums
-    launches += cell == RCU_GRU ? 16 : 15;
+    // 5 GEMMs, 4 or 5 transposes, prep, recurrence, 2 two-kernel column sums;
+    // projection: 3 GEMMs, 4 transposes, up to 2 adds
+    launches += (cell == RCU_GRU ? 16 : 15) + (P > 0 ? 7 + (dhnl ? 1 : 0) + (T > 1 ? 1 : 0) : 0);
     dYcur = dX;
     if (l > 0 && !dX) return fail(RCU_ERR_INVALID, "rnn_backward: internal");
   }
@@ -1143,20 +1196,21 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
 }
 
 extern "C" int rnn_get_weight_grads(rcu_rnn_t h, int layer, int dir, float *dW_ih, float *dW_hh,
-                                    float *db_ih, float *db_hh, void *stream) {
+                                    float *db_ih, float *db_hh, float *dW_hr, void *stream) {
   if (!h) return fail(RCU_ERR_INVALID, "rnn_get_weight_grads: NULL handle");
   if (!h->grads_ready) return fail(RCU_ERR_STATE, "rnn_get_weight_grads: no rnn_backward has run");
   if (layer < 0 || layer >= h->layers || dir != 0)
     return fail(RCU_ERR_INVALID, "rnn_get_weight_grads: layer %d / dir %d out of range", layer, dir);
+  if (dW_hr && h->P == 0) return fail(RCU_ERR_INVALID, "rnn_get_weight_grads: no projection");
   cudaStream_t s = (cudaStream_t)stream;
-  const int G = h->nG * h->H, K = h->in_l[layer], H = h->H;
+  const int G = h->nG * h->H, K = h->in_l[layer], Ho = h->Hout, P = h->P, H = h->H;
   const float *g = (const float *)h->gw[layer].p;
-  const float *src[4] = {g, g + (size_t)G * K, g + (size_t)G * K + (size_t)G * H,
-                         g + (size_t)G * K + (size_t)G * H + G};
-  float *dst[4] = {dW_ih, dW_hh, db_ih, db_hh};
-  const size_t n[4] = {(size_t)G * K, (size_t)G * H, (size_t)G, (size_t)G};
-  for (int i = 0; i < 4; ++i)
-    if (dst[i]) CU(cudaMemcpyAsync(dst[i], src[i], n[i] * 4, cudaMemcpyDefault, s));
+  const size_t o1 = (size_t)G * K, o2 = o1 + (size_t)G * Ho, o3 = o2 + G, o4 = o3 + G;
+  const float *src[5] = {g, g + o1, g + o2, g + o3, g + o4};
+  float *dst[5] = {dW_ih, dW_hh, db_ih, db_hh, dW_hr};
+  const size_t n[5] = {(size_t)G * K, (size_t)G * Ho, (size_t)G, (size_t)G, (size_t)P * H};
+  for (int i = 0; i < 5; ++i)
+    if (dst[i] && n[i]) CU(cudaMemcpyAsync(dst[i], src[i], n[i] * 4, cudaMemcpyDefault, s));
   return RCU_OK;
 }
 

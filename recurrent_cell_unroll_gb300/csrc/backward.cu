@@ -30,10 +30,11 @@ constexpr int NT = 512;
 
 // ---- activations and the LSTM cell scan.  zin holds X W_ih^T + b_ih on
 // entry and the activated gates on exit (LSTM i, f, g, o; GRU r, z, n);
-// zh = H_prev W_hh^T + b_hh is only read.  cs[t][b][u] = c_t (LSTM).
+// zh = H_prev W_hh^T + b_hh is only read.  cs[t][b][u] = c_t (LSTM);
+// ms[t][b][u] = m_t = o tanh(c_t) when ms is given (LSTM with projection).
 __global__ void bwd_prep_kernel(int T, int B, int H, int cell, float *__restrict__ zin,
                                 const float *__restrict__ zh, const float *__restrict__ c0,
-                                float *__restrict__ cs) {
+                                float *__restrict__ cs, float *__restrict__ ms) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= B * H) return;
   const int b = e / H, u = e % H;
@@ -50,6 +51,7 @@ __global__ void bwd_prep_kernel(int T, int B, int H, int cell, float *__restrict
       const float o = sigmoid_f(a[3 * H + u] + h[3 * H + u]);
       c = f * c + i * g;
       cs[r * H + u] = c;
+      if (ms) ms[r * H + u] = o * tanh_f(c);
       a[u] = i; a[H + u] = f; a[2 * H + u] = g; a[3 * H + u] = o;
     } else {
       const float rg = sigmoid_f(a[u] + h[u]);
@@ -341,9 +343,22 @@ RecPlan plan_rec(int H, int B, int nG, int nsm) {
 }  // namespace
 
 cudaError_t launch_bwd_prep(int T, int B, int H, int cell, float *zin, const float *zh,
-                            const float *c0, float *cs, cudaStream_t s) {
+                            const float *c0, float *cs, float *ms, cudaStream_t s) {
   const int n = B * H;
-  bwd_prep_kernel<<<ceil_div(n, 256), 256, 0, s>>>(T, B, H, cell, zin, zh, c0, cs);
+  bwd_prep_kernel<<<ceil_div(n, 256), 256, 0, s>>>(T, B, H, cell, zin, zh, c0, cs, ms);
+  return cudaGetLastError();
+}
+
+namespace {
+__global__ void add_kernel(float *__restrict__ dst, const float *__restrict__ src, size_t n) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) dst[i] += src[i];
+}
+}  // namespace
+
+cudaError_t launch_add(float *dst, const float *src, size_t n, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  add_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(dst, src, n);
   return cudaGetLastError();
 }
 

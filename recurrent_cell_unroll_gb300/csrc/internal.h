@@ -128,9 +128,12 @@ bool rssm_supported(int S, int A, int Hd, int RH, int Hx = 0);
 
 // ---- backward.cu: backward pass through time (fp32, unidirectional) ---------
 // zin: X W_ih^T + b_ih in, activated gates out; zh: H_prev W_hh^T + b_hh;
-// cs: LSTM cell sequence out.  Parallel over B*H, sequential over T.
+// cs: LSTM cell sequence out; ms: m_t = o tanh(c_t) out (projection) or NULL.
+// Parallel over B*H, sequential over T.
 cudaError_t launch_bwd_prep(int T, int B, int H, int cell, float *zin, const float *zh,
-                            const float *c0, float *cs, cudaStream_t s);
+                            const float *c0, float *cs, float *ms, cudaStream_t s);
+// dst[i] += src[i], i < n
+cudaError_t launch_add(float *dst, const float *src, size_t n, cudaStream_t s);
 struct BwdRecArgs {
   int T, B, H, cell;
   const float *Whh;  // [nG*H][ldw]

@@ -783,6 +783,10 @@ BWD_SPECS = [
     wl.GRU_3L.scaled(T=24, B=32, in_dim=128, hidden=256, layers=3, dtype="f32", h0_std=0.1),
     wl.LSTM_T80.scaled(T=1, B=1, in_dim=5, hidden=7, layers=2, c0_std=0.5, h0_std=0.5),
     wl.GRU_3L.scaled(T=9, B=130, in_dim=40, hidden=48, layers=1, dtype="f32", h0_std=0.0),
+    # LSTM with projection
+    wl.LSTMP_2L.scaled(T=6, B=5, in_dim=12, hidden=20, proj=8, dtype="f32", h0_std=0.5,
+                       c0_std=0.5),
+    wl.LSTMP_2L.scaled(T=16, B=32, in_dim=64, hidden=128, proj=32, dtype="f32"),
 ]
 
 
@@ -790,13 +794,14 @@ def _rel(a, b):
     return float(np.abs(a - b).max() / max(np.abs(b).max(), 1e-30))
 
 
-@pytest.mark.parametrize("spec", BWD_SPECS, ids=lambda s: f"{s.cell}-L{s.layers}-T{s.T}-B{s.B}-H{s.hidden}")
+@pytest.mark.parametrize("spec", BWD_SPECS,
+                         ids=lambda s: f"{s.cell}-L{s.layers}-T{s.T}-B{s.B}-H{s.hidden}-P{s.proj}")
 def test_backward_parity(spec):
     inp = wl.make_rnn_inputs(spec, seed=12)
     g = torch.Generator().manual_seed(99)
-    L, B, H = spec.layers, spec.B, spec.hidden
-    dy = torch.randn((spec.T, B, H), generator=g)
-    dhn = torch.randn((L, B, H), generator=g)
+    L, B, H, Ho = spec.layers, spec.B, spec.hidden, spec.Hout
+    dy = torch.randn((spec.T, B, Ho), generator=g)
+    dhn = torch.randn((L, B, Ho), generator=g)
     dcn = torch.randn((L, B, H), generator=g) if spec.cell == "lstm" else None
     dev = torch.device("cuda")
     net = binding.RNN.from_spec(spec)
@@ -808,13 +813,13 @@ def test_backward_parity(spec):
                                        dh_n=d(dhn), dc_n=d(dcn))
     torch.cuda.synchronize()
     assert net.status() == 0
-    ref = oracle.rnn_backward(_cell(spec), inp["x"], inp["weights"], dy, hidden=H, h0=inp["h0"],
-                              c0=inp["c0"], dh_n=dhn, dc_n=dcn)
+    ref = oracle.rnn_backward(_cell(spec), inp["x"], inp["weights"], dy, hidden=H,
+                              proj=spec.proj, h0=inp["h0"], c0=inp["c0"], dh_n=dhn, dc_n=dcn)
     pairs = [("dx", dx, ref["dx"]), ("dh0", dh0, ref["dh0"])]
     if spec.cell == "lstm":
         pairs.append(("dc0", dc0, ref["dc0"]))
     for layer in range(L):
-        for k in ("w_ih", "w_hh", "b_ih", "b_hh"):
+        for k in ("w_ih", "w_hh", "b_ih", "b_hh") + (("w_hr",) if spec.proj else ()):
             pairs.append((f"d{k}[{layer}]", grads[layer][k], ref["d" + k][layer]))
     for name, got, want in pairs:
         e = _rel(got.cpu().numpy().astype(np.float64), want)
@@ -832,7 +837,7 @@ def test_backward_errors():
     with pytest.raises(RuntimeError, match="no rnn_backward"):
         binding.rnn_get_weight_grads(net.h, 0, None, None, None, None)
     net.close()
-    for bad in (spec.scaled(dtype="bf16"), spec.scaled(bidir=True), spec.scaled(proj=8)):
+    for bad in (spec.scaled(dtype="bf16"), spec.scaled(bidir=True)):
         net = binding.RNN.from_spec(bad)
         net.set_weights(wl.make_rnn_inputs(bad, seed=1)["weights"])
         x = torch.zeros((bad.T, bad.B, bad.in_dim), device=dev)
