@@ -65,7 +65,7 @@ def _load():
             lib.oracle_rssm_unroll2.argtypes = ([i, i, i, i, i, i] + [P] * 14 + [P, P, P, P, P, i, i]
                                                 + [i, P, P, P, P, P])
             lib.oracle_rnn_backward.restype = i
-            lib.oracle_rnn_backward.argtypes = [i, i, i, i, i, i, i] + [P] * 15 + [i]
+            lib.oracle_rnn_backward.argtypes = [i] * 8 + [P] * 15 + [i]
             lib.oracle_bf16_round.restype = ctypes.c_double
             lib.oracle_bf16_round.argtypes = [ctypes.c_float]
             lib.oracle_num_threads_default.restype = i
@@ -168,57 +168,62 @@ def rnn_forward(cell: int, x, weights, *, hidden: int, proj: int = 0, bidirectio
     return y, hn, (cn if cell == LSTM else None)
 
 
-def rnn_backward(cell: int, x, weights, dy, *, hidden: int, proj: int = 0, h0=None, c0=None,
-                 dh_n=None, dc_n=None, threads: int = 0):
-    """Backward pass through time of a stacked unidirectional LSTM / GRU, or
-    LSTM with projection (no lengths or clipping), in fp64: the gradients of a
-    loss with dL/dy = dy [T,B,Ho] (and dL/dh_n [L,B,Ho], dL/dc_n [L,B,H],
-    None = 0; Ho = proj or hidden).
+def rnn_backward(cell: int, x, weights, dy, *, hidden: int, proj: int = 0,
+                 bidirectional: bool = False, h0=None, c0=None, dh_n=None, dc_n=None,
+                 threads: int = 0):
+    """Backward pass through time of a stacked LSTM / GRU, or LSTM with
+    projection, optionally bidirectional (no lengths or clipping), in fp64:
+    the gradients of a loss with dL/dy = dy [T,B,D*Ho] (and dL/dh_n
+    [L*D,B,Ho], dL/dc_n [L*D,B,H], None = 0; Ho = proj or hidden).
 
-    weights: list over layers of dicts w_ih, w_hh, b_ih, b_hh (None = zero) and
-    w_hr (projection).  Returns a dict: dx [T,B,in], dh0 [L,B,Ho], dc0 [L,B,H]
-    (LSTM, else None), and per-layer lists dw_ih, dw_hh, db_ih, db_hh, dw_hr
-    (None without projection) in the weights' shapes.
+    weights: list over layer*D + dir of dicts w_ih, w_hh, b_ih, b_hh (None =
+    zero) and w_hr (projection).  Returns a dict: dx [T,B,in], dh0
+    [L*D,B,Ho], dc0 [L*D,B,H] (LSTM, else None), and lists over layer*D + dir
+    of dw_ih, dw_hh, db_ih, db_hh, dw_hr (None without projection) in the
+    weights' shapes.
     """
     lib = _load()
     x = _f32(x)
     T, B, in_dim = x.shape
-    L = len(weights)
+    D = 2 if bidirectional else 1
+    LD = len(weights)
+    L = LD // D
+    assert L * D == LD and L >= 1
     H = hidden
     Ho = proj if proj > 0 else H
     nG = 4 if cell == LSTM else 3
     keep = []
-    arr = (_LayerW * L)()
+    arr = (_LayerW * LD)()
     for i, w in enumerate(weights):
         vals = [_f32(w.get(k)) for k in ("w_ih", "w_hh", "b_ih", "b_hh")] + \
             [_f32(w.get("w_hr")) if proj > 0 else None]
         keep.extend(vals)
         arr[i] = _LayerW(*[_ptr(v) for v in vals])
     h0a, c0a, dya, dhn, dcn = _f32(h0), _f32(c0), _f32(dy), _f32(dh_n), _f32(dc_n)
-    in_l = [in_dim] + [Ho] * (L - 1)
+    in_l = [in_dim if i // D == 0 else D * Ho for i in range(LD)]
     dx = np.zeros((T, B, in_dim))
-    dh0 = np.zeros((L, B, Ho))
-    dc0 = np.zeros((L, B, H))
+    dh0 = np.zeros((LD, B, Ho))
+    dc0 = np.zeros((LD, B, H))
     dwih = np.zeros(sum(nG * H * k for k in in_l))
-    dwhh = np.zeros(L * nG * H * Ho)
-    dbih = np.zeros(L * nG * H)
-    dbhh = np.zeros(L * nG * H)
-    dwhr = np.zeros(max(1, L * proj * H))
-    rc = lib.oracle_rnn_backward(int(cell), L, in_dim, H, int(proj), T, B, _ptr(x), _ptr(h0a),
-                                 _ptr(c0a), ctypes.addressof(arr), _ptr(dya), _ptr(dhn),
-                                 _ptr(dcn), _ptr(dx), _ptr(dh0), _ptr(dc0), _ptr(dwih),
-                                 _ptr(dwhh), _ptr(dbih), _ptr(dbhh),
+    dwhh = np.zeros(LD * nG * H * Ho)
+    dbih = np.zeros(LD * nG * H)
+    dbhh = np.zeros(LD * nG * H)
+    dwhr = np.zeros(max(1, LD * proj * H))
+    rc = lib.oracle_rnn_backward(int(cell), int(bidirectional), L, in_dim, H, int(proj), T, B,
+                                 _ptr(x), _ptr(h0a), _ptr(c0a), ctypes.addressof(arr), _ptr(dya),
+                                 _ptr(dhn), _ptr(dcn), _ptr(dx), _ptr(dh0), _ptr(dc0),
+                                 _ptr(dwih), _ptr(dwhh), _ptr(dbih), _ptr(dbhh),
                                  _ptr(dwhr) if proj > 0 else None, int(threads))
     if rc != 0:
         raise ValueError("oracle_rnn_backward: invalid arguments")
     offs = np.cumsum([0] + [nG * H * k for k in in_l])
     return {"dx": dx, "dh0": dh0, "dc0": dc0 if cell == LSTM else None,
-            "dw_ih": [dwih[offs[l]:offs[l + 1]].reshape(nG * H, in_l[l]) for l in range(L)],
-            "dw_hh": [dwhh[l * nG * H * Ho:(l + 1) * nG * H * Ho].reshape(nG * H, Ho)
-                      for l in range(L)],
-            "db_ih": [dbih[l * nG * H:(l + 1) * nG * H] for l in range(L)],
-            "db_hh": [dbhh[l * nG * H:(l + 1) * nG * H] for l in range(L)],
-            "dw_hr": [dwhr[l * proj * H:(l + 1) * proj * H].reshape(proj, H) for l in range(L)]
+            "dw_ih": [dwih[offs[i]:offs[i + 1]].reshape(nG * H, in_l[i]) for i in range(LD)],
+            "dw_hh": [dwhh[i * nG * H * Ho:(i + 1) * nG * H * Ho].reshape(nG * H, Ho)
+                      for i in range(LD)],
+            "db_ih": [dbih[i * nG * H:(i + 1) * nG * H] for i in range(LD)],
+            "db_hh": [dbhh[i * nG * H:(i + 1) * nG * H] for i in range(LD)],
+            "dw_hr": [dwhr[i * proj * H:(i + 1) * proj * H].reshape(proj, H) for i in range(LD)]
             if proj > 0 else None}
 
 

@@ -504,12 +504,16 @@ int oracle_num_threads_default(void) {
 /*     hidden side dR = [dr r(1-r), dz z(1-z), dhn]                         */
 /*     dx_t = W_ih^T dA;  dh' += W_hh^T dR;  dW_ih += dA x^T;              */
 /*     dW_hh += dR h'^T;  db_ih += dA;  db_hh += dR                          */
+/* Bidirectional: direction 1 runs its forward from t = T-1 down to 0, so   */
+/* its backward replays t = 0 .. T-1; layer l+1's input is [h_fwd, h_bwd]  */
+/* and both directions' input gradients add into layer l's dy.             */
 /* Layer l's dx is layer l-1's dy.  Weight gradients are summed over rows   */
-/* and steps; layouts follow the weights (layer l of dW_ih at offset        */
-/* sum_{j<l} nG*H*in_j, dW_hh at l*nG*H*Ho, db at l*nG*H, dW_hr at l*P*H).  */
-/* Outputs: dx [T,B,in], dh0 [L,B,Ho], dc0 [L,B,H] (LSTM; may be NULL).     */
-int oracle_rnn_backward(int cell, int layers, int in_dim, int hidden, int proj, int T, int B,
-                        const float *x, const float *h0, const float *c0,
+/* and steps; layouts follow the weights per (layer, direction) i = l*D + d */
+/* (dW_ih at offset sum_{j<i} nG*H*in_j, dW_hh at i*nG*H*Ho, db at i*nG*H,  */
+/* dW_hr at i*P*H).  Outputs: dx [T,B,in], dh0 [L*D,B,Ho], dc0 [L*D,B,H]    */
+/* (LSTM; may be NULL).                                                     */
+int oracle_rnn_backward(int cell, int bidir, int layers, int in_dim, int hidden, int proj, int T,
+                        int B, const float *x, const float *h0, const float *c0,
                         const oracle_layer_w *w, const float *dy, const float *dh_n,
                         const float *dc_n, double *dx, double *dh0, double *dc0, double *dW_ih,
                         double *dW_hh, double *db_ih, double *db_hh, double *dW_hr,
@@ -517,33 +521,35 @@ int oracle_rnn_backward(int cell, int layers, int in_dim, int hidden, int proj, 
     if (cell != OR_LSTM && cell != OR_GRU) return -1;
     if (layers < 1 || in_dim < 1 || hidden < 1 || T < 1 || B < 1 || !x || !dy) return -1;
     if (proj < 0 || (proj > 0 && cell != OR_LSTM)) return -1;
-    const int H = hidden, P = proj, Ho = proj > 0 ? proj : hidden;
+    const int D = bidir ? 2 : 1, LD = layers * D;
+    const int H = hidden, P = proj, Ho = proj > 0 ? proj : hidden, DHo = D * Ho;
     const int nG = (cell == OR_LSTM) ? 4 : 3, G = nG * H;
     const int lstm = cell == OR_LSTM;
-    size_t *off_ih = (size_t *)calloc((size_t)layers + 1, sizeof(size_t));
-    double **Wih = (double **)calloc(layers, sizeof(double *));
-    double **Whh = (double **)calloc(layers, sizeof(double *));
-    double **bih = (double **)calloc(layers, sizeof(double *));
-    double **bhh = (double **)calloc(layers, sizeof(double *));
-    double **Whr = (double **)calloc(layers, sizeof(double *));
-    for (int l = 0; l < layers; ++l) {
-        const int in_w = l == 0 ? in_dim : Ho;
-        off_ih[l + 1] = off_ih[l] + (size_t)G * in_w;
-        Wih[l] = widen(w[l].w_ih, (size_t)G * in_w, 0);
-        Whh[l] = widen(w[l].w_hh, (size_t)G * Ho, 0);
-        bih[l] = widen(w[l].b_ih, (size_t)G, 0);
-        bhh[l] = widen(w[l].b_hh, (size_t)G, 0);
-        Whr[l] = P > 0 ? widen(w[l].w_hr, (size_t)P * H, 0) : NULL;
+    /* per (layer, direction) i = l*D + d */
+    size_t *off_ih = (size_t *)calloc((size_t)LD + 1, sizeof(size_t));
+    double **Wih = (double **)calloc(LD, sizeof(double *));
+    double **Whh = (double **)calloc(LD, sizeof(double *));
+    double **bih = (double **)calloc(LD, sizeof(double *));
+    double **bhh = (double **)calloc(LD, sizeof(double *));
+    double **Whr = (double **)calloc(LD, sizeof(double *));
+    for (int i = 0; i < LD; ++i) {
+        const int in_w = i / D == 0 ? in_dim : DHo;
+        off_ih[i + 1] = off_ih[i] + (size_t)G * in_w;
+        Wih[i] = widen(w[i].w_ih, (size_t)G * in_w, 0);
+        Whh[i] = widen(w[i].w_hh, (size_t)G * Ho, 0);
+        bih[i] = widen(w[i].b_ih, (size_t)G, 0);
+        bhh[i] = widen(w[i].b_hh, (size_t)G, 0);
+        Whr[i] = P > 0 ? widen(w[i].w_hr, (size_t)P * H, 0) : NULL;
     }
-    const int wmax = in_dim > Ho ? in_dim : Ho;
+    const int wmax = in_dim > DHo ? in_dim : DHo;
     int nth = 1;
 #ifdef _OPENMP
     if (nthreads > 0) omp_set_num_threads(nthreads);
     nth = omp_get_max_threads();
 #endif
     /* per-thread weight-gradient accumulators, summed in thread order at the end */
-    const size_t n_ih = off_ih[layers], n_hh = (size_t)layers * G * Ho, n_b = (size_t)layers * G,
-                 n_hr = (size_t)layers * P * H;
+    const size_t n_ih = off_ih[LD], n_hh = (size_t)LD * G * Ho, n_b = (size_t)LD * G,
+                 n_hr = (size_t)LD * P * H;
     const size_t nw = n_ih + n_hh + 2 * n_b + n_hr;
     double *acc = (double *)calloc((size_t)nth * nw, sizeof(double));
 #ifdef _OPENMP
@@ -559,14 +565,15 @@ int oracle_rnn_backward(int cell, int layers, int in_dim, int hidden, int proj, 
         double *gbih = gWhh + n_hh;
         double *gbhh = gbih + n_b;
         double *gWhr = gbhh + n_b;
-        /* per row: every layer's input sequence, h_t (t = -1 .. T-1), c_t, m_t, gates */
+        /* per row: every layer's input sequence [T][wmax]; per (layer, dir) and
+           processing step s: h (s = -1 .. T-1), c, m, gates */
         double *X = (double *)malloc((size_t)layers * T * wmax * sizeof(double));
-        double *hs = (double *)malloc((size_t)layers * (T + 1) * Ho * sizeof(double));
-        double *cs = (double *)malloc((size_t)layers * (T + 1) * H * sizeof(double));
-        double *ms = (double *)malloc((size_t)layers * T * H * sizeof(double));
-        double *gt = (double *)malloc((size_t)layers * T * (G + H) * sizeof(double));
+        double *hs = (double *)malloc((size_t)LD * (T + 1) * Ho * sizeof(double));
+        double *cs = (double *)malloc((size_t)LD * (T + 1) * H * sizeof(double));
+        double *ms = (double *)malloc((size_t)LD * T * H * sizeof(double));
+        double *gt = (double *)malloc((size_t)LD * T * (G + H) * sizeof(double));
         double *dX = (double *)malloc((size_t)T * wmax * sizeof(double));
-        double *dY = (double *)malloc((size_t)T * Ho * sizeof(double));
+        double *dY = (double *)malloc((size_t)T * DHo * sizeof(double));
         double *dh = (double *)malloc((size_t)Ho * sizeof(double));
         double *dm = (double *)malloc((size_t)H * sizeof(double));
         double *dc = (double *)malloc((size_t)H * sizeof(double));
@@ -583,139 +590,149 @@ int oracle_rnn_backward(int cell, int layers, int in_dim, int hidden, int proj, 
                 for (int k = 0; k < in_dim; ++k)
                     X[(size_t)t * wmax + k] = (double)x[((size_t)t * B + b) * in_dim + k];
             for (int l = 0; l < layers; ++l) {
-                const int in_w = l == 0 ? in_dim : Ho;
+                const int in_w = l == 0 ? in_dim : DHo;
                 const double *Xl = X + (size_t)l * T * wmax;
-                double *hl = hs + (size_t)l * (T + 1) * Ho, *cl = cs + (size_t)l * (T + 1) * H;
-                double *ml = ms + (size_t)l * T * H;
-                double *gl = gt + (size_t)l * T * (G + H);
-                for (int k = 0; k < Ho; ++k) hl[k] = h0 ? (double)h0[((size_t)l * B + b) * Ho + k] : 0.0;
-                for (int k = 0; k < H; ++k)
-                    cl[k] = (lstm && c0) ? (double)c0[((size_t)l * B + b) * H + k] : 0.0;
-                for (int t = 0; t < T; ++t) {
-                    const double *xt = Xl + (size_t)t * wmax, *hp = hl + (size_t)t * Ho;
-                    double *hn_ = hl + (size_t)(t + 1) * Ho, *cn_ = cl + (size_t)(t + 1) * H;
-                    double *mt = ml + (size_t)t * H;
-                    double *g = gl + (size_t)t * (G + H);
-                    for (int n = 0; n < G; ++n) {
-                        double a = bih[l][n], r = bhh[l][n];
-                        for (int k = 0; k < in_w; ++k) a += Wih[l][(size_t)n * in_w + k] * xt[k];
-                        for (int k = 0; k < Ho; ++k) r += Whh[l][(size_t)n * Ho + k] * hp[k];
-                        pre[n] = a;
-                        pre[G + n] = r;
-                    }
-                    for (int u = 0; u < H; ++u) {
-                        if (lstm) {
-                            const double i = sigmoid(pre[u] + pre[G + u]);
-                            const double f = sigmoid(pre[H + u] + pre[G + H + u]);
-                            const double gg = tanh(pre[2 * H + u] + pre[G + 2 * H + u]);
-                            const double o = sigmoid(pre[3 * H + u] + pre[G + 3 * H + u]);
-                            cn_[u] = f * cl[(size_t)t * H + u] + i * gg;
-                            mt[u] = o * tanh(cn_[u]);
-                            g[u] = i; g[H + u] = f; g[2 * H + u] = gg; g[3 * H + u] = o;
+                for (int d = 0; d < D; ++d) {
+                    const int i = l * D + d;
+                    double *hl = hs + (size_t)i * (T + 1) * Ho, *cl = cs + (size_t)i * (T + 1) * H;
+                    double *ml = ms + (size_t)i * T * H;
+                    double *gl = gt + (size_t)i * T * (G + H);
+                    for (int k = 0; k < Ho; ++k) hl[k] = h0 ? (double)h0[((size_t)i * B + b) * Ho + k] : 0.0;
+                    for (int k = 0; k < H; ++k)
+                        cl[k] = (lstm && c0) ? (double)c0[((size_t)i * B + b) * H + k] : 0.0;
+                    for (int s2 = 0; s2 < T; ++s2) {
+                        const int t = d == 0 ? s2 : T - 1 - s2;
+                        const double *xt = Xl + (size_t)t * wmax, *hp = hl + (size_t)s2 * Ho;
+                        double *hn_ = hl + (size_t)(s2 + 1) * Ho, *cn_ = cl + (size_t)(s2 + 1) * H;
+                        double *mt = ml + (size_t)s2 * H;
+                        double *g = gl + (size_t)s2 * (G + H);
+                        for (int n = 0; n < G; ++n) {
+                            double a = bih[i][n], r = bhh[i][n];
+                            for (int k = 0; k < in_w; ++k) a += Wih[i][(size_t)n * in_w + k] * xt[k];
+                            for (int k = 0; k < Ho; ++k) r += Whh[i][(size_t)n * Ho + k] * hp[k];
+                            pre[n] = a;
+                            pre[G + n] = r;
+                        }
+                        for (int u = 0; u < H; ++u) {
+                            if (lstm) {
+                                const double ig = sigmoid(pre[u] + pre[G + u]);
+                                const double f = sigmoid(pre[H + u] + pre[G + H + u]);
+                                const double gg = tanh(pre[2 * H + u] + pre[G + 2 * H + u]);
+                                const double o = sigmoid(pre[3 * H + u] + pre[G + 3 * H + u]);
+                                cn_[u] = f * cl[(size_t)s2 * H + u] + ig * gg;
+                                mt[u] = o * tanh(cn_[u]);
+                                g[u] = ig; g[H + u] = f; g[2 * H + u] = gg; g[3 * H + u] = o;
+                            } else {
+                                const double r = sigmoid(pre[u] + pre[G + u]);
+                                const double z = sigmoid(pre[H + u] + pre[G + H + u]);
+                                const double hnp = pre[G + 2 * H + u];  /* W_hn h' + b_hn */
+                                const double n = tanh(pre[2 * H + u] + r * hnp);
+                                mt[u] = (1.0 - z) * n + z * hp[u];
+                                cn_[u] = 0.0;
+                                g[u] = r; g[H + u] = z; g[2 * H + u] = n; g[G + u] = hnp;
+                            }
+                        }
+                        if (P > 0) {
+                            for (int q = 0; q < P; ++q) {
+                                double a2 = 0.0;
+                                for (int k = 0; k < H; ++k) a2 += Whr[i][(size_t)q * H + k] * mt[k];
+                                hn_[q] = a2;
+                            }
                         } else {
-                            const double r = sigmoid(pre[u] + pre[G + u]);
-                            const double z = sigmoid(pre[H + u] + pre[G + H + u]);
-                            const double hnp = pre[G + 2 * H + u];  /* W_hn h' + b_hn */
-                            const double n = tanh(pre[2 * H + u] + r * hnp);
-                            mt[u] = (1.0 - z) * n + z * hp[u];
-                            cn_[u] = 0.0;
-                            g[u] = r; g[H + u] = z; g[2 * H + u] = n; g[G + u] = hnp;
+                            memcpy(hn_, mt, (size_t)H * sizeof(double));
                         }
+                        if (l + 1 < layers)  /* next layer input at time t: [h_fwd || h_bwd] */
+                            memcpy(X + ((size_t)(l + 1) * T + t) * wmax + (size_t)d * Ho, hn_,
+                                   (size_t)Ho * sizeof(double));
                     }
-                    if (P > 0) {
-                        for (int q = 0; q < P; ++q) {
-                            double s2 = 0.0;
-                            for (int k = 0; k < H; ++k) s2 += Whr[l][(size_t)q * H + k] * mt[k];
-                            hn_[q] = s2;
-                        }
-                    } else {
-                        memcpy(hn_, mt, (size_t)H * sizeof(double));
-                    }
-                    if (l + 1 < layers)
-                        memcpy(X + ((size_t)(l + 1) * T + t) * wmax, hn_, (size_t)Ho * sizeof(double));
                 }
             }
-            /* ---- backward, top layer first */
+            /* ---- backward, top layer first; direction d replays its steps in reverse */
             for (int t = 0; t < T; ++t)
-                for (int k = 0; k < Ho; ++k) dY[(size_t)t * Ho + k] = (double)dy[((size_t)t * B + b) * Ho + k];
+                for (int k = 0; k < DHo; ++k) dY[(size_t)t * DHo + k] = (double)dy[((size_t)t * B + b) * DHo + k];
             for (int l = layers - 1; l >= 0; --l) {
-                const int in_w = l == 0 ? in_dim : Ho;
+                const int in_w = l == 0 ? in_dim : DHo;
                 const double *Xl = X + (size_t)l * T * wmax;
-                const double *hl = hs + (size_t)l * (T + 1) * Ho, *cl = cs + (size_t)l * (T + 1) * H;
-                const double *ml = ms + (size_t)l * T * H;
-                const double *gl = gt + (size_t)l * T * (G + H);
-                for (int k = 0; k < Ho; ++k) dhp[k] = dh_n ? (double)dh_n[((size_t)l * B + b) * Ho + k] : 0.0;
-                for (int k = 0; k < H; ++k)
-                    dc[k] = (lstm && dc_n) ? (double)dc_n[((size_t)l * B + b) * H + k] : 0.0;
-                for (int t = T - 1; t >= 0; --t) {
-                    const double *g = gl + (size_t)t * (G + H);
-                    const double *hp = hl + (size_t)t * Ho, *xt = Xl + (size_t)t * wmax;
-                    const double *mt = ml + (size_t)t * H;
-                    for (int q = 0; q < Ho; ++q) dh[q] = dY[(size_t)t * Ho + q] + dhp[q];
-                    if (P > 0) {
-                        double *gWr = gWhr + (size_t)l * P * H;
-                        for (int k = 0; k < H; ++k) {
-                            double s2 = 0.0;
-                            for (int q = 0; q < P; ++q) s2 += Whr[l][(size_t)q * H + k] * dh[q];
-                            dm[k] = s2;
-                        }
-                        for (int q = 0; q < P; ++q)
-                            for (int k = 0; k < H; ++k) gWr[(size_t)q * H + k] += dh[q] * mt[k];
-                    } else {
-                        memcpy(dm, dh, (size_t)H * sizeof(double));
-                    }
-                    for (int u = 0; u < H; ++u) {
-                        if (lstm) {
-                            const double i = g[u], f = g[H + u], gg = g[2 * H + u], o = g[3 * H + u];
-                            const double c = cl[(size_t)(t + 1) * H + u], cp = cl[(size_t)t * H + u];
-                            const double tc = tanh(c);
-                            const double dcu = dc[u] + dm[u] * o * (1.0 - tc * tc);
-                            dA[u] = dcu * gg * i * (1.0 - i);
-                            dA[H + u] = dcu * cp * f * (1.0 - f);
-                            dA[2 * H + u] = dcu * i * (1.0 - gg * gg);
-                            dA[3 * H + u] = dm[u] * tc * o * (1.0 - o);
-                            dc[u] = dcu * f;
-                            dR[u] = dA[u]; dR[H + u] = dA[H + u];
-                            dR[2 * H + u] = dA[2 * H + u]; dR[3 * H + u] = dA[3 * H + u];
+                for (size_t e = 0; e < (size_t)T * wmax; ++e) dX[e] = 0.0;
+                for (int d = 0; d < D; ++d) {
+                    const int i = l * D + d;
+                    const double *hl = hs + (size_t)i * (T + 1) * Ho, *cl = cs + (size_t)i * (T + 1) * H;
+                    const double *ml = ms + (size_t)i * T * H;
+                    const double *gl = gt + (size_t)i * T * (G + H);
+                    for (int k = 0; k < Ho; ++k) dhp[k] = dh_n ? (double)dh_n[((size_t)i * B + b) * Ho + k] : 0.0;
+                    for (int k = 0; k < H; ++k)
+                        dc[k] = (lstm && dc_n) ? (double)dc_n[((size_t)i * B + b) * H + k] : 0.0;
+                    for (int s2 = T - 1; s2 >= 0; --s2) {
+                        const int t = d == 0 ? s2 : T - 1 - s2;
+                        const double *g = gl + (size_t)s2 * (G + H);
+                        const double *hp = hl + (size_t)s2 * Ho, *xt = Xl + (size_t)t * wmax;
+                        const double *mt = ml + (size_t)s2 * H;
+                        for (int q = 0; q < Ho; ++q) dh[q] = dY[(size_t)t * DHo + (size_t)d * Ho + q] + dhp[q];
+                        if (P > 0) {
+                            double *gWr = gWhr + (size_t)i * P * H;
+                            for (int k = 0; k < H; ++k) {
+                                double a2 = 0.0;
+                                for (int q = 0; q < P; ++q) a2 += Whr[i][(size_t)q * H + k] * dh[q];
+                                dm[k] = a2;
+                            }
+                            for (int q = 0; q < P; ++q)
+                                for (int k = 0; k < H; ++k) gWr[(size_t)q * H + k] += dh[q] * mt[k];
                         } else {
-                            const double r = g[u], z = g[H + u], n = g[2 * H + u], hnp = g[G + u];
-                            const double dn = dm[u] * (1.0 - z);
-                            const double dz = dm[u] * (hp[u] - n);
-                            const double dan = dn * (1.0 - n * n);
-                            const double dr = dan * hnp;
-                            dA[u] = dr * r * (1.0 - r);
-                            dA[H + u] = dz * z * (1.0 - z);
-                            dA[2 * H + u] = dan;
-                            dR[u] = dA[u]; dR[H + u] = dA[H + u];
-                            dR[2 * H + u] = dan * r;
+                            memcpy(dm, dh, (size_t)H * sizeof(double));
+                        }
+                        for (int u = 0; u < H; ++u) {
+                            if (lstm) {
+                                const double ig = g[u], f = g[H + u], gg = g[2 * H + u], o = g[3 * H + u];
+                                const double c = cl[(size_t)(s2 + 1) * H + u], cp = cl[(size_t)s2 * H + u];
+                                const double tc = tanh(c);
+                                const double dcu = dc[u] + dm[u] * o * (1.0 - tc * tc);
+                                dA[u] = dcu * gg * ig * (1.0 - ig);
+                                dA[H + u] = dcu * cp * f * (1.0 - f);
+                                dA[2 * H + u] = dcu * ig * (1.0 - gg * gg);
+                                dA[3 * H + u] = dm[u] * tc * o * (1.0 - o);
+                                dc[u] = dcu * f;
+                                dR[u] = dA[u]; dR[H + u] = dA[H + u];
+                                dR[2 * H + u] = dA[2 * H + u]; dR[3 * H + u] = dA[3 * H + u];
+                            } else {
+                                const double r = g[u], z = g[H + u], n = g[2 * H + u], hnp = g[G + u];
+                                const double dn = dm[u] * (1.0 - z);
+                                const double dz = dm[u] * (hp[u] - n);
+                                const double dan = dn * (1.0 - n * n);
+                                const double dr = dan * hnp;
+                                dA[u] = dr * r * (1.0 - r);
+                                dA[H + u] = dz * z * (1.0 - z);
+                                dA[2 * H + u] = dan;
+                                dR[u] = dA[u]; dR[H + u] = dA[H + u];
+                                dR[2 * H + u] = dan * r;
+                            }
+                        }
+                        /* gradients of this step's weights, input and previous state */
+                        double *gWi = gWih + off_ih[i], *gWh = gWhh + (size_t)i * G * Ho;
+                        for (int n = 0; n < G; ++n) {
+                            for (int k = 0; k < in_w; ++k) gWi[(size_t)n * in_w + k] += dA[n] * xt[k];
+                            for (int k = 0; k < Ho; ++k) gWh[(size_t)n * Ho + k] += dR[n] * hp[k];
+                            gbih[(size_t)i * G + n] += dA[n];
+                            gbhh[(size_t)i * G + n] += dR[n];
+                        }
+                        for (int k = 0; k < in_w; ++k) {
+                            double a2 = 0.0;
+                            for (int n = 0; n < G; ++n) a2 += Wih[i][(size_t)n * in_w + k] * dA[n];
+                            dX[(size_t)t * wmax + k] += a2;
+                        }
+                        for (int k = 0; k < Ho; ++k) {
+                            double a2 = lstm ? 0.0 : dm[k] * g[H + k];  /* GRU: direct path z h' */
+                            for (int n = 0; n < G; ++n) a2 += Whh[i][(size_t)n * Ho + k] * dR[n];
+                            dhp[k] = a2;
                         }
                     }
-                    /* gradients of this step's weights, input and previous state */
-                    double *gWi = gWih + off_ih[l], *gWh = gWhh + (size_t)l * G * Ho;
-                    for (int n = 0; n < G; ++n) {
-                        for (int k = 0; k < in_w; ++k) gWi[(size_t)n * in_w + k] += dA[n] * xt[k];
-                        for (int k = 0; k < Ho; ++k) gWh[(size_t)n * Ho + k] += dR[n] * hp[k];
-                        gbih[(size_t)l * G + n] += dA[n];
-                        gbhh[(size_t)l * G + n] += dR[n];
-                    }
-                    for (int k = 0; k < in_w; ++k) {
-                        double s2 = 0.0;
-                        for (int n = 0; n < G; ++n) s2 += Wih[l][(size_t)n * in_w + k] * dA[n];
-                        dX[(size_t)t * wmax + k] = s2;
-                    }
-                    for (int k = 0; k < Ho; ++k) {
-                        double s2 = lstm ? 0.0 : dm[k] * g[H + k];  /* GRU: direct path z h' */
-                        for (int n = 0; n < G; ++n) s2 += Whh[l][(size_t)n * Ho + k] * dR[n];
-                        dhp[k] = s2;
-                    }
+                    for (int k = 0; k < Ho; ++k)
+                        if (dh0) dh0[((size_t)i * B + b) * Ho + k] = dhp[k];
+                    for (int k = 0; k < H; ++k)
+                        if (dc0 && lstm) dc0[((size_t)i * B + b) * H + k] = dc[k];
                 }
-                for (int k = 0; k < Ho; ++k)
-                    if (dh0) dh0[((size_t)l * B + b) * Ho + k] = dhp[k];
-                for (int k = 0; k < H; ++k)
-                    if (dc0 && lstm) dc0[((size_t)l * B + b) * H + k] = dc[k];
                 if (l > 0) {
                     for (int t = 0; t < T; ++t)
-                        memcpy(dY + (size_t)t * Ho, dX + (size_t)t * wmax, (size_t)Ho * sizeof(double));
+                        memcpy(dY + (size_t)t * DHo, dX + (size_t)t * wmax, (size_t)DHo * sizeof(double));
                 } else if (dx) {
                     for (int t = 0; t < T; ++t)
                         for (int k = 0; k < in_dim; ++k)
@@ -733,15 +750,15 @@ int oracle_rnn_backward(int cell, int layers, int in_dim, int hidden, int proj, 
     for (int j = 0; j < 5; ++j) {
         if (outs[j])
             for (size_t e = 0; e < lens[j]; ++e) {
-                double s2 = 0.0;
-                for (int q = 0; q < nth; ++q) s2 += acc[(size_t)q * nw + base + e];
-                outs[j][e] = s2;
+                double a2 = 0.0;
+                for (int q = 0; q < nth; ++q) a2 += acc[(size_t)q * nw + base + e];
+                outs[j][e] = a2;
             }
         base += lens[j];
     }
     free(acc);
-    for (int l = 0; l < layers; ++l) {
-        free(Wih[l]); free(Whh[l]); free(bih[l]); free(bhh[l]); free(Whr[l]);
+    for (int i = 0; i < LD; ++i) {
+        free(Wih[i]); free(Whh[i]); free(bih[i]); free(bhh[i]); free(Whr[i]);
     }
     free(Wih); free(Whh); free(bih); free(bhh); free(Whr); free(off_ih);
     return 0;

@@ -849,3 +849,93 @@ def test_bptt_projection_finite_differences():
                 want = g[gk][layer][idx]
                 assert abs(fd - want) <= 1e-5 * max(1.0, abs(want)), (layer, k, idx, fd, want)
 
+
+
+@pytest.mark.parametrize("cell,layers,proj", [(oracle.LSTM, 2, 0), (oracle.GRU, 2, 0),
+                                              (oracle.LSTM, 2, 3), (oracle.LSTM, 1, 0)])
+def test_bptt_bidirectional_against_torch_autograd(cell, layers, proj):
+    """Bidirectional stacks: the oracle's gradients equal torch float64
+    autograd through nn.LSTM / nn.GRU(bidirectional=True)."""
+    rng = np.random.default_rng(60 + layers + 3 * cell + proj)
+    T, B, in_dim, H = 5, 3, 4, 5
+    Ho = proj or H
+    D = 2
+    ws = _rand_weights(rng, cell, layers, in_dim, H, D=D, proj=proj)
+    x = rng.standard_normal((T, B, in_dim)).astype(np.float32)
+    h0 = (0.5 * rng.standard_normal((layers * D, B, Ho))).astype(np.float32)
+    c0 = (0.5 * rng.standard_normal((layers * D, B, H))).astype(np.float32)
+    dy = rng.standard_normal((T, B, D * Ho)).astype(np.float32)
+    dhn = rng.standard_normal((layers * D, B, Ho)).astype(np.float32)
+    dcn = rng.standard_normal((layers * D, B, H)).astype(np.float32)
+    lstm = cell == oracle.LSTM
+    g = oracle.rnn_backward(cell, x, ws, dy, hidden=H, proj=proj, bidirectional=True, h0=h0,
+                            c0=c0 if lstm else None, dh_n=dhn, dc_n=dcn if lstm else None)
+    kw = dict(input_size=in_dim, hidden_size=H, num_layers=layers, bidirectional=True,
+              dtype=torch.float64)
+    mod = torch.nn.LSTM(proj_size=proj, **kw) if lstm else torch.nn.GRU(**kw)
+    names = (("w_ih", "weight_ih"), ("w_hh", "weight_hh"), ("b_ih", "bias_ih"),
+             ("b_hh", "bias_hh")) + ((("w_hr", "weight_hr"),) if proj else ())
+    with torch.no_grad():
+        for layer in range(layers):
+            for d in range(D):
+                sfx = f"_l{layer}" + ("_reverse" if d else "")
+                for k, name in names:
+                    getattr(mod, name + sfx).copy_(torch.from_numpy(ws[layer * D + d][k]).double())
+    xt = torch.from_numpy(x).double().requires_grad_()
+    ht = torch.from_numpy(h0).double().requires_grad_()
+    if lstm:
+        ct = torch.from_numpy(c0).double().requires_grad_()
+        y, (hn, cn) = mod(xt, (ht, ct))
+        loss = (y * torch.from_numpy(dy).double()).sum() + \
+            (hn * torch.from_numpy(dhn).double()).sum() + (cn * torch.from_numpy(dcn).double()).sum()
+    else:
+        y, hn = mod(xt, ht)
+        loss = (y * torch.from_numpy(dy).double()).sum() + (hn * torch.from_numpy(dhn).double()).sum()
+    loss.backward()
+    tol = dict(rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(g["dx"], xt.grad.numpy(), **tol)
+    np.testing.assert_allclose(g["dh0"], ht.grad.numpy(), **tol)
+    if lstm:
+        np.testing.assert_allclose(g["dc0"], ct.grad.numpy(), **tol)
+    for layer in range(layers):
+        for d in range(D):
+            sfx = f"_l{layer}" + ("_reverse" if d else "")
+            for k, name in names:
+                np.testing.assert_allclose(g["d" + k][layer * D + d],
+                                           getattr(mod, name + sfx).grad.numpy(), **tol,
+                                           err_msg=f"d{k}{sfx}")
+
+
+def test_bptt_bidirectional_finite_differences():
+    rng = np.random.default_rng(77)
+    T, B, in_dim, H, layers, D = 4, 2, 3, 4, 2, 2
+    ws = _rand_weights(rng, oracle.GRU, layers, in_dim, H, D=D)
+    x = rng.standard_normal((T, B, in_dim)).astype(np.float32)
+    h0 = (0.5 * rng.standard_normal((layers * D, B, H))).astype(np.float32)
+    dy = rng.standard_normal((T, B, D * H)).astype(np.float32)
+
+    def loss(x_, ws_):
+        y, _, _ = oracle.rnn_forward(oracle.GRU, x_, ws_, hidden=H, bidirectional=True, h0=h0)
+        return float((y * dy).sum())
+
+    g = oracle.rnn_backward(oracle.GRU, x, ws, dy, hidden=H, bidirectional=True, h0=h0)
+    eps = np.float32(2.0 ** -10)
+    for idx in ((0, 0, 0), (T - 1, B - 1, in_dim - 1), (2, 1, 1)):
+        hi, lo = x.copy(), x.copy()
+        hi[idx] += eps
+        lo[idx] -= eps
+        fd = (loss(hi, ws) - loss(lo, ws)) / (2 * float(eps))
+        assert abs(fd - g["dx"][idx]) <= 1e-5 * max(1.0, abs(g["dx"][idx])), (idx, fd)
+    for i in range(layers * D):
+        arr = ws[i]["w_hh"]
+        for idx in ((0, 0), (arr.shape[0] - 1, arr.shape[1] - 1)):
+            hi, lo = arr.copy(), arr.copy()
+            hi[idx] += eps
+            lo[idx] -= eps
+            w_hi = [dict(w) for w in ws]
+            w_lo = [dict(w) for w in ws]
+            w_hi[i]["w_hh"] = hi
+            w_lo[i]["w_hh"] = lo
+            fd = (loss(x, w_hi) - loss(x, w_lo)) / (2 * float(eps))
+            want = g["dw_hh"][i][idx]
+            assert abs(fd - want) <= 1e-5 * max(1.0, abs(want)), (i, idx, fd, want)
