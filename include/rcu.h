@@ -199,14 +199,15 @@ RCU_API int rnn_forward_host(rcu_rnn_t h, int T, int B, const float *x, const in
  * Backward pass through time (BPTT), the training use of the unrolled cell
  * ("[Feature Request] CUDNN version of RSSM", pytorch/rl issue 366,
  * Motivation; "Integrating CuDNN API for LSTMs with projections",
- * pytorch/pytorch issue 46213, training discussion).  fp32 handles,
- * unidirectional, without lengths or clipping (else RCU_ERR_UNSUPPORTED);
- * LSTM with projection included.  Given the forward's inputs x [T,B,in],
- * h0 [L,B,Hout] / c0 [L,B,H] (or NULL) and the gradient of a loss with
- * respect to y, dy [T,B,Hout] (and to h_n / c_n, dh_n [L,B,Hout] / dc_n
- * [L,B,H] or NULL = 0), writes the gradients dx [T,B,in], dh0 [L,B,Hout] and
- * dc0 [L,B,H] (LSTM) — each may be NULL — and keeps the weight gradients of
- * every layer, summed over rows and steps, for rnn_get_weight_grads.  All
+ * pytorch/pytorch issue 46213, training discussion).  fp32 handles without
+ * lengths or clipping (else RCU_ERR_UNSUPPORTED): LSTM, GRU and LSTM with
+ * projection, uni- or bidirectional.  Given the forward's inputs x [T,B,in],
+ * h0 [L*D,B,Hout] / c0 [L*D,B,H] (or NULL) and the gradient of a loss with
+ * respect to y, dy [T,B,D*Hout] (and to h_n / c_n, dh_n [L*D,B,Hout] / dc_n
+ * [L*D,B,H] or NULL = 0), writes the gradients dx [T,B,in], dh0 [L*D,B,Hout]
+ * and dc0 [L*D,B,H] (LSTM) — each may be NULL — and keeps the weight
+ * gradients of every layer and direction, summed over rows and steps, for
+ * rnn_get_weight_grads.  All
  * device pointers; asynchronous on `stream`; a device-side failure is
  * reported by rnn_get_status.
  * The forward is recomputed inside the call (every layer's output sequence
@@ -217,7 +218,7 @@ RCU_API int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const float 
                          const float *c0, const float *dy, const float *dh_n, const float *dc_n,
                          float *dx, float *dh0, float *dc0, void *stream);
 /*
- * Weight gradients of layer `layer` (dir 0) from the last rnn_backward, in the
+ * Weight gradients of layer `layer`, direction `dir` from the last rnn_backward, in the
  * weights' own layout: dW_ih [nG*H, in_l], dW_hh [nG*H, Hout], db_ih, db_hh
  * [nG*H], dW_hr [P, H] (projection only; must be NULL without one).  Any of
  * them may be NULL.  RCU_ERR_STATE before any rnn_backward.

@@ -268,9 +268,11 @@ def rnn_backward(h, T: int, B: int, x, h0, c0, dy, dh_n, dc_n, dx, dh0, dc0, str
                                _stream(stream)))
 
 
-def rnn_get_weight_grads(h, layer: int, dW_ih, dW_hh, db_ih, db_hh, dW_hr=None, stream=None):
+def rnn_get_weight_grads(h, layer: int, dW_ih, dW_hh, db_ih, db_hh, dW_hr=None, stream=None,
+                         direction: int = 0):
     outs = [_dev(t) for t in (dW_ih, dW_hh, db_ih, db_hh, dW_hr)]
-    _check(load().rnn_get_weight_grads(h, layer, 0, *[k[1] for k in outs], _stream(stream)))
+    _check(load().rnn_get_weight_grads(h, layer, direction, *[k[1] for k in outs],
+                                       _stream(stream)))
 
 
 def rssm_create(state_dim: int, action_dim: int, hidden: int, rnn_hidden: int):
@@ -389,21 +391,22 @@ class RNN:
         T, B, in_dim = x.shape
         dev = x.device
         dx = torch.empty_like(x)
-        dh0 = torch.empty((self.layers, B, self.Hout), device=dev)
-        dc0 = torch.empty((self.layers, B, self.hidden), device=dev) \
-            if self.cell == "lstm" else None
+        LD = self.layers * self.D
+        dh0 = torch.empty((LD, B, self.Hout), device=dev)
+        dc0 = torch.empty((LD, B, self.hidden), device=dev) if self.cell == "lstm" else None
         rnn_backward(self.h, T, B, x, h0, c0, dy, dh_n, dc_n, dx, dh0, dc0, stream)
         nG = 4 if self.cell == "lstm" else 3
-        grads = []
-        for layer in range(self.layers):
-            k = in_dim if layer == 0 else self.Hout
+        grads = []  # over layer * D + direction, like the weights
+        for i in range(LD):
+            layer, d = divmod(i, self.D)
+            k = in_dim if layer == 0 else self.D * self.Hout
             g = {"w_ih": torch.empty((nG * self.hidden, k), device=dev),
                  "w_hh": torch.empty((nG * self.hidden, self.Hout), device=dev),
                  "b_ih": torch.empty((nG * self.hidden,), device=dev),
                  "b_hh": torch.empty((nG * self.hidden,), device=dev),
                  "w_hr": torch.empty((self.proj, self.hidden), device=dev) if self.proj else None}
             rnn_get_weight_grads(self.h, layer, g["w_ih"], g["w_hh"], g["b_ih"], g["b_hh"],
-                                 g["w_hr"], stream)
+                                 g["w_hr"], stream, direction=d)
             grads.append(g)
         return dx, dh0, dc0, grads
 

@@ -1020,37 +1020,43 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
   h->launches = 0;
   for (auto &w : h->lw)
     if (!w.set) return fail(RCU_ERR_STATE, "rnn_backward: weights missing for some layer/direction");
-  if (h->dtype != RCU_F32 || h->D != 1 || h->cclip || h->pclip)
-    return fail(RCU_ERR_UNSUPPORTED, "rnn_backward: fp32 unidirectional networks without clipping");
+  if (h->dtype != RCU_F32 || h->cclip || h->pclip)
+    return fail(RCU_ERR_UNSUPPORTED, "rnn_backward: fp32 networks without clipping");
   if (T < 1 || B < 1 || !x || !dy) return fail(RCU_ERR_INVALID, "rnn_backward: need T, B >= 1, x and dy");
   if (h->cell == RCU_GRU && (c0 || dc_n || dc0))
     return fail(RCU_ERR_INVALID, "rnn_backward: c0/dc_n/dc0 are LSTM-only");
   if ((size_t)T * B > (size_t)INT32_MAX / 8)
     return fail(RCU_ERR_UNSUPPORTED, "rnn_backward: T*B too large");
-  const int L = h->layers, H = h->H, nG = h->nG, G = nG * H, cell = h->cell;
-  const int P = h->P, Ho = h->Hout;
+  const int L = h->layers, D = h->D, H = h->H, nG = h->nG, G = nG * H, cell = h->cell;
+  const int P = h->P, Ho = h->Hout, DHo = D * Ho;
   if (bwd_units_per_cta(H, B, nG, h->nsm) < 1)
     return fail(RCU_ERR_UNSUPPORTED, "rnn_backward: W_hh columns do not fit one SM per unit group");
   cudaStream_t s = (cudaStream_t)stream;
   const int M = T * B;
-  const size_t TBH = (size_t)M * H, TBO = (size_t)M * Ho, TBG = (size_t)M * G;
+  const size_t TBH = (size_t)M * H, TBO = (size_t)M * Ho, TBY = (size_t)M * DHo,
+               TBG = (size_t)M * G;
   const int ldh = round_up(H, 8), ldo = round_up(Ho, 8);
-  int kmax = std::max(H, Ho);
+  int kmax = std::max(H, DHo);
   for (int l = 0; l < L; ++l) kmax = std::max(kmax, h->in_l[l]);
+  const size_t TBK = (size_t)M * kmax;
   // ---- workspace (floats; every piece 256-byte aligned)
   size_t off = 0;
   auto take = [&](size_t n) { size_t r = off; off += (n + 63) & ~size_t(63); return r; };
-  const size_t o_keep = take((size_t)L * TBO), o_hp = take(TBO), o_zin = take(TBG),
+  const size_t o_keep = take((size_t)L * TBY), o_hp = take(TBO), o_zin = take(TBG),
                o_zh = take(TBG), o_cs = take(cell == RCU_LSTM ? TBH : 0), o_da = take(TBG),
-               o_dr = take(cell == RCU_GRU ? TBG : 0), o_dya = take(TBO), o_dyb = take(TBO),
-               o_t1 = take(TBG), o_t2 = take((size_t)M * kmax),
-               o_t3 = take(cell == RCU_GRU ? TBG : 0), o_t4 = take(TBO),
-               o_wt = take((size_t)kmax * G), o_cs2 = take(colsum_scratch_floats(M, G)),
+               o_dr = take(cell == RCU_GRU ? TBG : 0), o_dya = take(TBY), o_dyb = take(TBY),
+               o_t1 = take(TBG), o_t2 = take(TBK), o_t3 = take(cell == RCU_GRU ? TBG : 0),
+               o_t4 = take(TBO), o_wt = take((size_t)kmax * G),
+               o_cs2 = take(colsum_scratch_floats(M, G)),
                // projection only
                o_ms = take(P ? TBH : 0), o_dyp = take(P ? TBO : 0), o_a = take(P ? TBH : 0),
                o_f = take(P ? (size_t)G * ldh : 0), o_whrt = take(P ? (size_t)H * P : 0),
                o_whht = take(P ? (size_t)Ho * G : 0), o_r = take(P ? TBO : 0),
-               o_t5 = take(P ? TBH : 0), o_t6 = take(P ? TBO : 0), o_ctl = take(64);
+               o_t5 = take(P ? TBH : 0), o_t6 = take(P ? TBO : 0),
+               // bidirectional only: processing-order copies of one direction
+               o_xr = take(D > 1 ? TBK : 0), o_yd = take(D > 1 ? TBO : 0),
+               o_dyd = take(D > 1 ? TBO : 0), o_dxr = take(D > 1 ? TBK : 0),
+               o_tmp = take(D > 1 ? TBK : 0), o_ctl = take(64);
   CU(h->bw.ensure(off * 4));
   float *wsf = (float *)h->bw.p;
   float *keep = wsf + o_keep, *hp = wsf + o_hp, *zin = wsf + o_zin, *zh = wsf + o_zh;
@@ -1062,53 +1068,58 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
   float *ms = P ? wsf + o_ms : nullptr, *dYp = wsf + o_dyp, *Aw = wsf + o_a, *Fw = wsf + o_f;
   float *WhrT = wsf + o_whrt, *WhhT = wsf + o_whht, *Rw = wsf + o_r, *T5 = wsf + o_t5,
         *T6 = wsf + o_t6;
+  float *XR = wsf + o_xr, *YD = wsf + o_yd, *DYD = wsf + o_dyd, *DXR = wsf + o_dxr,
+        *TMP = wsf + o_tmp;
   unsigned *ctr = (unsigned *)(wsf + o_ctl);
-  if ((int)h->gw.size() < L) h->gw.resize(L);
+  if ((int)h->gw.size() < L * D) h->gw.resize((size_t)L * D);
   h->grads_ready = false;
   int launches = 0;
   // ---- forward again, keeping every layer's output sequence
   h->keep_out = keep;
-  int rc = rnn_forward(h, T, B, x, nullptr, h0, c0, nullptr, keep + (size_t)(L - 1) * TBO,
+  int rc = rnn_forward(h, T, B, x, nullptr, h0, c0, nullptr, keep + (size_t)(L - 1) * TBY,
                        nullptr, nullptr, stream);
   h->keep_out = nullptr;
   if (rc != RCU_OK) return rc;
   launches += h->launches;
   // the handle's error word (cleared by the forward above), read by rnn_get_status
   int *err = (int *)h->ctl.p;
-  const float *dYcur = dy;
-  for (int l = L - 1; l >= 0; --l) {
-    const int K = h->in_l[l], ldk = round_up(K, 8);
-    const LayerDirW &lw = h->lw[(size_t)l];
-    const float *X = l == 0 ? x : keep + (size_t)(l - 1) * TBO;
-    float *dX = l == 0 ? dx : (dYcur == dYa ? dYb : dYa);
-    const float *dhnl = dh_n ? dh_n + (size_t)l * B * Ho : nullptr;
+
+  // One (layer, direction) i = l*D + d, on inputs in its processing order (the
+  // reverse direction's sequences are time-reversed copies, so it is an
+  // ordinary forward recurrence): X [M][K], its output sequence Y [M][Ho],
+  // dY [M][Ho]; writes dX [M][K] (may be NULL) and the weight gradients.
+  auto run_dir = [&](int l, int d, const float *X, int K, const float *Y, const float *dYdir,
+                     float *dX) -> int {
+    const int i = l * D + d, ldk = round_up(K, 8);
+    const LayerDirW &lw = h->lw[(size_t)i];
+    const float *Wih = (const float *)h->wih[l].p + (size_t)d * G * ldk;
+    const float *dhnl = dh_n ? dh_n + (size_t)i * B * Ho : nullptr;
     // h_{t-1} for t = 0 .. T-1
-    if (h0) CU(cudaMemcpyAsync(hp, h0 + (size_t)l * B * Ho, (size_t)B * Ho * 4, cudaMemcpyDeviceToDevice, s));
+    if (h0) CU(cudaMemcpyAsync(hp, h0 + (size_t)i * B * Ho, (size_t)B * Ho * 4, cudaMemcpyDeviceToDevice, s));
     else CU(cudaMemsetAsync(hp, 0, (size_t)B * Ho * 4, s));
     if (T > 1)
-      CU(cudaMemcpyAsync(hp + (size_t)B * Ho, keep + (size_t)l * TBO, (size_t)(T - 1) * B * Ho * 4,
+      CU(cudaMemcpyAsync(hp + (size_t)B * Ho, Y, (size_t)(T - 1) * B * Ho * 4,
                          cudaMemcpyDeviceToDevice, s));
     // pre-activations of every step
     h->begin("bwd_recompute_gemm", s);
-    cudaError_t e = launch_gemm_simt<float, float>(X, K, (const float *)h->wih[l].p, ldk,
-                                                   (const float *)lw.bih_plain.p, zin, G, M,
-                                                   nullptr, G, K, s, err);
+    cudaError_t e = launch_gemm_simt<float, float>(X, K, Wih, ldk, (const float *)lw.bih_plain.p,
+                                                   zin, G, M, nullptr, G, K, s, err);
     if (e == cudaSuccess)
       e = launch_gemm_simt<float, float>(hp, Ho, (const float *)lw.whh_plain.p, ldo,
                                          (const float *)lw.bhh_plain.p, zh, G, M, nullptr, G, Ho,
                                          s, err);
     h->end(s);
-    const float *c0l = c0 ? c0 + (size_t)l * B * H : nullptr;
+    const float *c0l = c0 ? c0 + (size_t)i * B * H : nullptr;
     h->begin("bwd_prep", s);
     if (e == cudaSuccess) e = launch_bwd_prep(T, B, H, cell, zin, zh, c0l, cs, ms, s);
     h->end(s);
     if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: recompute: %s", cudaGetErrorString(e));
     // projection: dy' = dy (+ dh_n at the last step), A = dy' W_hr, F = W_hh W_hr
-    const float *rec_dy = dYcur, *rec_W = (const float *)lw.whh_plain.p;
+    const float *rec_dy = dYdir, *rec_W = (const float *)lw.whh_plain.p;
     int rec_ldw = ldo;
     if (P > 0) {
       h->begin("bwd_proj_fold", s);
-      CU(cudaMemcpyAsync(dYp, dYcur, TBO * 4, cudaMemcpyDeviceToDevice, s));
+      CU(cudaMemcpyAsync(dYp, dYdir, TBO * 4, cudaMemcpyDeviceToDevice, s));
       if (dhnl) e = launch_add(dYp + (size_t)(T - 1) * B * Ho, dhnl, (size_t)B * Ho, s);
       if (e == cudaSuccess) e = launch_transpose((const float *)lw.whr_plain.p, P, H, H, WhrT, P, s);
       if (e == cudaSuccess)
@@ -1129,17 +1140,17 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
     a.Whh = rec_W; a.ldw = rec_ldw;
     a.gates = zin; a.zh = zh; a.cs = cs; a.c0 = c0l; a.hp = hp; a.dy = rec_dy;
     a.dhn = P > 0 ? nullptr : dhnl;
-    a.dcn = dc_n ? dc_n + (size_t)l * B * H : nullptr;
+    a.dcn = dc_n ? dc_n + (size_t)i * B * H : nullptr;
     a.DA = DA; a.DR = DR;
-    a.dh0 = (P > 0 || !dh0) ? nullptr : dh0 + (size_t)l * B * H;
-    a.dc0 = dc0 ? dc0 + (size_t)l * B * H : nullptr;
+    a.dh0 = (P > 0 || !dh0) ? nullptr : dh0 + (size_t)i * B * H;
+    a.dc0 = dc0 ? dc0 + (size_t)i * B * H : nullptr;
     a.ctr = ctr; a.err = err; a.timeout_ns = (uint64_t)h->timeout_ns;
-    a.drop_arrival = h->drop_arrival == 2 && l == L - 1;
+    a.drop_arrival = h->drop_arrival == 2 && l == L - 1 && d == 0;
     h->begin("bwd_recurrent", s);
     e = launch_bwd_rec(a, h->nsm, s);
     h->end(s);
     if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: recurrence: %s", cudaGetErrorString(e));
-    DevBuf &g = h->gw[l];
+    DevBuf &g = h->gw[(size_t)i];
     CU(g.ensure(((size_t)G * K + (size_t)G * Ho + 2 * (size_t)G + (size_t)P * H) * 4));
     float *gWih = (float *)g.p, *gWhh = gWih + (size_t)G * K, *gbih = gWhh + (size_t)G * Ho,
           *gbhh = gbih + G, *gWhr = gbhh + G;
@@ -1151,7 +1162,7 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
       if (e == cudaSuccess)
         e = launch_gemm_simt<float, float>(DA, G, WhhT, G, nullptr, Rw, Ho, M, nullptr, Ho, G, s, err);
       if (e == cudaSuccess && dh0)
-        e = cudaMemcpyAsync(dh0 + (size_t)l * B * Ho, Rw, (size_t)B * Ho * 4, cudaMemcpyDeviceToDevice, s);
+        e = cudaMemcpyAsync(dh0 + (size_t)i * B * Ho, Rw, (size_t)B * Ho * 4, cudaMemcpyDeviceToDevice, s);
       if (e == cudaSuccess && T > 1) e = launch_add(dYp, Rw + (size_t)B * Ho, (size_t)(T - 1) * B * Ho, s);
       if (e == cudaSuccess) e = launch_transpose(dYp, M, Ho, Ho, T6, M, s);
       if (e == cudaSuccess) e = launch_transpose(ms, M, H, H, T5, M, s);
@@ -1167,7 +1178,7 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
     if (e == cudaSuccess) e = launch_transpose(X, M, K, K, T2, M, s);
     if (e == cudaSuccess && cell == RCU_GRU) e = launch_transpose(DR, M, G, G, T3, M, s);
     if (e == cudaSuccess) e = launch_transpose(hp, M, Ho, Ho, T4, M, s);
-    if (e == cudaSuccess) e = launch_transpose((const float *)h->wih[l].p, G, K, ldk, WT, G, s);
+    if (e == cudaSuccess) e = launch_transpose(Wih, G, K, ldk, WT, G, s);
     h->end(s);
     h->begin("bwd_weight_gemm", s);
     if (e == cudaSuccess)
@@ -1187,8 +1198,41 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
     // 5 GEMMs, 4 or 5 transposes, prep, recurrence, 2 two-kernel column sums;
     // projection: 3 GEMMs, 4 transposes, up to 2 adds
     launches += (cell == RCU_GRU ? 16 : 15) + (P > 0 ? 7 + (dhnl ? 1 : 0) + (T > 1 ? 1 : 0) : 0);
-    dYcur = dX;
-    if (l > 0 && !dX) return fail(RCU_ERR_INVALID, "rnn_backward: internal");
+    return RCU_OK;
+  };
+
+  const float *dYcur = dy;
+  for (int l = L - 1; l >= 0; --l) {
+    const int K = h->in_l[l];
+    const float *Xl = l == 0 ? x : keep + (size_t)(l - 1) * TBY;
+    const float *Yl = keep + (size_t)l * TBY;
+    float *dXl = l == 0 ? dx : (dYcur == dYa ? dYb : dYa);
+    if (l > 0 && !dXl) return fail(RCU_ERR_INVALID, "rnn_backward: internal");
+    if (D == 1) {
+      if (int r = run_dir(l, 0, Xl, K, Yl, dYcur, dXl)) return r;
+    } else {
+      for (int d = 0; d < 2; ++d) {
+        // direction d's sequences in its processing order
+        h->begin("bwd_reorder", s);
+        cudaError_t e = launch_gather_steps(Yl, DHo, d * Ho, Ho, T, B, d == 1, YD, s);
+        if (e == cudaSuccess) e = launch_gather_steps(dYcur, DHo, d * Ho, Ho, T, B, d == 1, DYD, s);
+        if (e == cudaSuccess && d == 1) e = launch_gather_steps(Xl, K, 0, K, T, B, true, XR, s);
+        h->end(s);
+        if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: reorder: %s", cudaGetErrorString(e));
+        launches += d == 1 ? 3 : 2;
+        float *dXd = dXl ? (d == 0 ? dXl : DXR) : nullptr;
+        if (int r = run_dir(l, d, d == 1 ? XR : Xl, K, YD, DYD, dXd)) return r;
+        if (d == 1 && dXl) {  // dX of the layer input: the forward one plus the reversed backward one
+          h->begin("bwd_reorder", s);
+          e = launch_gather_steps(DXR, K, 0, K, T, B, true, TMP, s);
+          if (e == cudaSuccess) e = launch_add(dXl, TMP, (size_t)M * K, s);
+          h->end(s);
+          if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: reorder: %s", cudaGetErrorString(e));
+          launches += 2;
+        }
+      }
+    }
+    dYcur = dXl;
   }
   h->grads_ready = true;
   h->launches = launches;
@@ -1199,12 +1243,12 @@ extern "C" int rnn_get_weight_grads(rcu_rnn_t h, int layer, int dir, float *dW_i
                                     float *db_ih, float *db_hh, float *dW_hr, void *stream) {
   if (!h) return fail(RCU_ERR_INVALID, "rnn_get_weight_grads: NULL handle");
   if (!h->grads_ready) return fail(RCU_ERR_STATE, "rnn_get_weight_grads: no rnn_backward has run");
-  if (layer < 0 || layer >= h->layers || dir != 0)
+  if (layer < 0 || layer >= h->layers || dir < 0 || dir >= h->D)
     return fail(RCU_ERR_INVALID, "rnn_get_weight_grads: layer %d / dir %d out of range", layer, dir);
   if (dW_hr && h->P == 0) return fail(RCU_ERR_INVALID, "rnn_get_weight_grads: no projection");
   cudaStream_t s = (cudaStream_t)stream;
   const int G = h->nG * h->H, K = h->in_l[layer], Ho = h->Hout, P = h->P, H = h->H;
-  const float *g = (const float *)h->gw[layer].p;
+  const float *g = (const float *)h->gw[(size_t)layer * h->D + dir].p;
   const size_t o1 = (size_t)G * K, o2 = o1 + (size_t)G * Ho, o3 = o2 + G, o4 = o3 + G;
   const float *src[5] = {g, g + o1, g + o2, g + o3, g + o4};
   float *dst[5] = {dW_ih, dW_hh, db_ih, db_hh, dW_hr};

@@ -356,6 +356,31 @@ __global__ void add_kernel(float *__restrict__ dst, const float *__restrict__ sr
 }
 }  // namespace
 
+namespace {
+// out[s][b][c] = in[t][b][col0 + c], t = reverse ? T-1-s : s (row stride ldi)
+__global__ void gather_steps_kernel(const float *__restrict__ in, int ldi, int col0, int w, int T,
+                                    int B, int reverse, float *__restrict__ out) {
+  const size_t n = (size_t)T * B * w;
+  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (size_t)gridDim.x * blockDim.x) {
+    const int c = (int)(e % w);
+    const size_t row = e / w;  // s * B + b
+    const int sidx = (int)(row / B), b = (int)(row % B);
+    const int t = reverse ? T - 1 - sidx : sidx;
+    out[e] = in[((size_t)t * B + b) * ldi + col0 + c];
+  }
+}
+}  // namespace
+
+cudaError_t launch_gather_steps(const float *in, int ldi, int col0, int w, int T, int B,
+                                bool reverse, float *out, cudaStream_t s) {
+  const size_t n = (size_t)T * B * w;
+  if (n == 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, 65535u * 8);
+  gather_steps_kernel<<<blocks, 256, 0, s>>>(in, ldi, col0, w, T, B, reverse ? 1 : 0, out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_add(float *dst, const float *src, size_t n, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   add_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(dst, src, n);

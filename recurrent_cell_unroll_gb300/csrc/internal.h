@@ -134,6 +134,10 @@ cudaError_t launch_bwd_prep(int T, int B, int H, int cell, float *zin, const flo
                             const float *c0, float *cs, float *ms, cudaStream_t s);
 // dst[i] += src[i], i < n
 cudaError_t launch_add(float *dst, const float *src, size_t n, cudaStream_t s);
+// out[s][b][0..w) = in[t][b][col0 .. col0+w) with t = s, or T-1-s when reversed
+// (in: row stride ldi per (t, b); out: contiguous [T][B][w])
+cudaError_t launch_gather_steps(const float *in, int ldi, int col0, int w, int T, int B,
+                                bool reverse, float *out, cudaStream_t s);
 struct BwdRecArgs {
   int T, B, H, cell;
   const float *Whh;  // [nG*H][ldw]

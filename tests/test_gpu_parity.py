@@ -787,6 +787,13 @@ BWD_SPECS = [
     wl.LSTMP_2L.scaled(T=6, B=5, in_dim=12, hidden=20, proj=8, dtype="f32", h0_std=0.5,
                        c0_std=0.5),
     wl.LSTMP_2L.scaled(T=16, B=32, in_dim=64, hidden=128, proj=32, dtype="f32"),
+    # bidirectional
+    wl.BILSTM_VAR.scaled(T=7, B=5, in_dim=12, hidden=20, layers=2, varlen=None, h0_std=0.5,
+                         c0_std=0.5),
+    wl.GRU_3L.scaled(T=6, B=9, in_dim=16, hidden=24, layers=2, dtype="f32", bidir=True),
+    wl.LSTMP_2L.scaled(T=5, B=4, in_dim=8, hidden=16, proj=6, dtype="f32", bidir=True,
+                       h0_std=0.5),
+    wl.BILSTM_VAR.scaled(T=32, B=64, in_dim=256, hidden=256, varlen=None),
 ]
 
 
@@ -795,14 +802,14 @@ def _rel(a, b):
 
 
 @pytest.mark.parametrize("spec", BWD_SPECS,
-                         ids=lambda s: f"{s.cell}-L{s.layers}-T{s.T}-B{s.B}-H{s.hidden}-P{s.proj}")
+                         ids=lambda s: f"{s.cell}-L{s.layers}-D{s.D}-T{s.T}-B{s.B}-H{s.hidden}-P{s.proj}")
 def test_backward_parity(spec):
     inp = wl.make_rnn_inputs(spec, seed=12)
     g = torch.Generator().manual_seed(99)
-    L, B, H, Ho = spec.layers, spec.B, spec.hidden, spec.Hout
-    dy = torch.randn((spec.T, B, Ho), generator=g)
-    dhn = torch.randn((L, B, Ho), generator=g)
-    dcn = torch.randn((L, B, H), generator=g) if spec.cell == "lstm" else None
+    L, B, H, Ho, D = spec.layers, spec.B, spec.hidden, spec.Hout, spec.D
+    dy = torch.randn((spec.T, B, D * Ho), generator=g)
+    dhn = torch.randn((L * D, B, Ho), generator=g)
+    dcn = torch.randn((L * D, B, H), generator=g) if spec.cell == "lstm" else None
     dev = torch.device("cuda")
     net = binding.RNN.from_spec(spec)
     net.set_weights(inp["weights"])
@@ -814,13 +821,14 @@ def test_backward_parity(spec):
     torch.cuda.synchronize()
     assert net.status() == 0
     ref = oracle.rnn_backward(_cell(spec), inp["x"], inp["weights"], dy, hidden=H,
-                              proj=spec.proj, h0=inp["h0"], c0=inp["c0"], dh_n=dhn, dc_n=dcn)
+                              proj=spec.proj, bidirectional=spec.bidir, h0=inp["h0"],
+                              c0=inp["c0"], dh_n=dhn, dc_n=dcn)
     pairs = [("dx", dx, ref["dx"]), ("dh0", dh0, ref["dh0"])]
     if spec.cell == "lstm":
         pairs.append(("dc0", dc0, ref["dc0"]))
-    for layer in range(L):
+    for i in range(L * D):
         for k in ("w_ih", "w_hh", "b_ih", "b_hh") + (("w_hr",) if spec.proj else ()):
-            pairs.append((f"d{k}[{layer}]", grads[layer][k], ref["d" + k][layer]))
+            pairs.append((f"d{k}[{i}]", grads[i][k], ref["d" + k][i]))
     for name, got, want in pairs:
         e = _rel(got.cpu().numpy().astype(np.float64), want)
         print(f"{name}: rel {e:.2e}")
@@ -837,12 +845,12 @@ def test_backward_errors():
     with pytest.raises(RuntimeError, match="no rnn_backward"):
         binding.rnn_get_weight_grads(net.h, 0, None, None, None, None)
     net.close()
-    for bad in (spec.scaled(dtype="bf16"), spec.scaled(bidir=True)):
+    for bad in (spec.scaled(dtype="bf16"),):
         net = binding.RNN.from_spec(bad)
         net.set_weights(wl.make_rnn_inputs(bad, seed=1)["weights"])
         x = torch.zeros((bad.T, bad.B, bad.in_dim), device=dev)
         dy = torch.zeros((bad.T, bad.B, bad.D * bad.Hout), device=dev)
-        with pytest.raises(RuntimeError, match="fp32 unidirectional"):
+        with pytest.raises(RuntimeError, match="fp32 networks"):
             binding.rnn_backward(net.h, bad.T, bad.B, x, None, None, dy, None, None, None, None,
                                  None)
         net.close()
