@@ -65,7 +65,7 @@ def _load():
             lib.oracle_rssm_unroll2.argtypes = ([i, i, i, i, i, i] + [P] * 14 + [P, P, P, P, P, i, i]
                                                 + [i, P, P, P, P, P])
             lib.oracle_rnn_backward.restype = i
-            lib.oracle_rnn_backward.argtypes = [i] * 8 + [P] * 15 + [i]
+            lib.oracle_rnn_backward.argtypes = [i] * 9 + [P] * 15 + [i]
             lib.oracle_bf16_round.restype = ctypes.c_double
             lib.oracle_bf16_round.argtypes = [ctypes.c_float]
             lib.oracle_num_threads_default.restype = i
@@ -170,7 +170,7 @@ def rnn_forward(cell: int, x, weights, *, hidden: int, proj: int = 0, bidirectio
 
 def rnn_backward(cell: int, x, weights, dy, *, hidden: int, proj: int = 0,
                  bidirectional: bool = False, h0=None, c0=None, dh_n=None, dc_n=None,
-                 threads: int = 0):
+                 bf16_weights: bool = False, threads: int = 0):
     """Backward pass through time of a stacked LSTM / GRU, or LSTM with
     projection, optionally bidirectional (no lengths or clipping), in fp64:
     the gradients of a loss with dL/dy = dy [T,B,D*Ho] (and dL/dh_n
@@ -180,7 +180,8 @@ def rnn_backward(cell: int, x, weights, dy, *, hidden: int, proj: int = 0,
     zero) and w_hr (projection).  Returns a dict: dx [T,B,in], dh0
     [L*D,B,Ho], dc0 [L*D,B,H] (LSTM, else None), and lists over layer*D + dir
     of dw_ih, dw_hh, db_ih, db_hh, dw_hr (None without projection) in the
-    weights' shapes.
+    weights' shapes.  bf16_weights: the weight matrices are rounded to bf16
+    first (biases stay fp32), as in rnn_forward.
     """
     lib = _load()
     x = _f32(x)
@@ -209,7 +210,8 @@ def rnn_backward(cell: int, x, weights, dy, *, hidden: int, proj: int = 0,
     dbih = np.zeros(LD * nG * H)
     dbhh = np.zeros(LD * nG * H)
     dwhr = np.zeros(max(1, LD * proj * H))
-    rc = lib.oracle_rnn_backward(int(cell), int(bidirectional), L, in_dim, H, int(proj), T, B,
+    rc = lib.oracle_rnn_backward(int(cell), int(bidirectional), L, in_dim, H, int(proj),
+                                 int(bool(bf16_weights)), T, B,
                                  _ptr(x), _ptr(h0a), _ptr(c0a), ctypes.addressof(arr), _ptr(dya),
                                  _ptr(dhn), _ptr(dcn), _ptr(dx), _ptr(dh0), _ptr(dc0),
                                  _ptr(dwih), _ptr(dwhh), _ptr(dbih), _ptr(dbhh),

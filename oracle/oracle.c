@@ -511,9 +511,10 @@ int oracle_num_threads_default(void) {
 /* and steps; layouts follow the weights per (layer, direction) i = l*D + d */
 /* (dW_ih at offset sum_{j<i} nG*H*in_j, dW_hh at i*nG*H*Ho, db at i*nG*H,  */
 /* dW_hr at i*P*H).  Outputs: dx [T,B,in], dh0 [L*D,B,Ho], dc0 [L*D,B,H]    */
-/* (LSTM; may be NULL).                                                     */
-int oracle_rnn_backward(int cell, int bidir, int layers, int in_dim, int hidden, int proj, int T,
-                        int B, const float *x, const float *h0, const float *c0,
+/* (LSTM; may be NULL).  bf16_weights: the weight matrices are first rounded */
+/* to bf16 (the forward oracle's convention; biases stay fp32).             */
+int oracle_rnn_backward(int cell, int bidir, int layers, int in_dim, int hidden, int proj,
+                        int bf16_weights, int T, int B, const float *x, const float *h0, const float *c0,
                         const oracle_layer_w *w, const float *dy, const float *dh_n,
                         const float *dc_n, double *dx, double *dh0, double *dc0, double *dW_ih,
                         double *dW_hh, double *db_ih, double *db_hh, double *dW_hr,
@@ -535,11 +536,12 @@ int oracle_rnn_backward(int cell, int bidir, int layers, int in_dim, int hidden,
     for (int i = 0; i < LD; ++i) {
         const int in_w = i / D == 0 ? in_dim : DHo;
         off_ih[i + 1] = off_ih[i] + (size_t)G * in_w;
-        Wih[i] = widen(w[i].w_ih, (size_t)G * in_w, 0);
-        Whh[i] = widen(w[i].w_hh, (size_t)G * Ho, 0);
+        Wih[i] = widen(w[i].w_ih, (size_t)G * in_w, bf16_weights);
+        Whh[i] = widen(w[i].w_hh, (size_t)G * Ho, bf16_weights);
+        /* biases stay fp32 on both paths */
         bih[i] = widen(w[i].b_ih, (size_t)G, 0);
         bhh[i] = widen(w[i].b_hh, (size_t)G, 0);
-        Whr[i] = P > 0 ? widen(w[i].w_hr, (size_t)P * H, 0) : NULL;
+        Whr[i] = P > 0 ? widen(w[i].w_hr, (size_t)P * H, bf16_weights) : NULL;
     }
     const int wmax = in_dim > DHo ? in_dim : DHo;
     int nth = 1;

@@ -939,3 +939,24 @@ def test_bptt_bidirectional_finite_differences():
             fd = (loss(x, w_hi) - loss(x, w_lo)) / (2 * float(eps))
             want = g["dw_hh"][i][idx]
             assert abs(fd - want) <= 1e-5 * max(1.0, abs(want)), (i, idx, fd, want)
+
+
+def test_bptt_bf16_weights_is_fp32_bptt_of_rounded_weights():
+    """bf16_weights rounds the weight matrices (not the biases) and nothing
+    else: equal, bit for bit, to the fp64 BPTT of pre-rounded weights."""
+    rng = np.random.default_rng(90)
+    T, B, in_dim, H, P = 4, 3, 5, 6, 3
+    ws = _rand_weights(rng, oracle.LSTM, 2, in_dim, H, proj=P)
+    rnd = [{k: (v if k in ("b_ih", "b_hh") or v is None else
+                torch.from_numpy(v).to(torch.bfloat16).float().numpy())
+            for k, v in w.items()} for w in ws]
+    x = rng.standard_normal((T, B, in_dim)).astype(np.float32)
+    dy = rng.standard_normal((T, B, P)).astype(np.float32)
+    a = oracle.rnn_backward(oracle.LSTM, x, ws, dy, hidden=H, proj=P, bf16_weights=True)
+    b = oracle.rnn_backward(oracle.LSTM, x, rnd, dy, hidden=H, proj=P)
+    for k in ("dx", "dh0", "dc0"):
+        assert np.array_equal(a[k], b[k]), k
+    for k in ("dw_ih", "dw_hh", "db_ih", "db_hh", "dw_hr"):
+        for u, v in zip(a[k], b[k]):
+            assert np.array_equal(u, v), k
+
