@@ -199,9 +199,10 @@ RCU_API int rnn_forward_host(rcu_rnn_t h, int T, int B, const float *x, const in
  * Backward pass through time (BPTT), the training use of the unrolled cell
  * ("[Feature Request] CUDNN version of RSSM", pytorch/rl issue 366,
  * Motivation; "Integrating CuDNN API for LSTMs with projections",
- * pytorch/pytorch issue 46213, training discussion).  fp32 handles without
- * lengths or clipping (else RCU_ERR_UNSUPPORTED): LSTM, GRU and LSTM with
- * projection, uni- or bidirectional.  Given the forward's inputs x [T,B,in],
+ * pytorch/pytorch issue 46213, training discussion).  Handles without lengths
+ * or clipping (else RCU_ERR_UNSUPPORTED): LSTM, GRU and LSTM with
+ * projection, uni- or bidirectional; on an RCU_BF16 handle, the fp32
+ * gradient of the model with the bf16-rounded weights its forward uses.  Given the forward's inputs x [T,B,in],
  * h0 [L*D,B,Hout] / c0 [L*D,B,H] (or NULL) and the gradient of a loss with
  * respect to y, dy [T,B,D*Hout] (and to h_n / c_n, dh_n [L*D,B,Hout] / dc_n
  * [L*D,B,H] or NULL = 0), writes the gradients dx [T,B,in], dh0 [L*D,B,Hout]

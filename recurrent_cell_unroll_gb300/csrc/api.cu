@@ -182,6 +182,7 @@ struct rcu_rnn_s {
   int U, NU, Rp, Kp, Hp, Pc, Pcp, NP;
   std::vector<int> in_l;         // GEMM K per layer
   std::vector<DevBuf> wih;       // [D*nG*H][ldk] per layer (dtype), ldk = round_up(in_l, 8)
+  std::vector<DevBuf> wih_f32;   // bf16 handles: the same, fp32 of the rounded values (backward)
   std::vector<DevBuf> gbias;     // [D*nG*H] fp32 per layer
   std::vector<std::vector<float>> host_bias; // staging: per layer, filled by set_weights
   std::vector<LayerDirW> lw;     // layers*D
@@ -336,6 +337,7 @@ extern "C" int rnn_create(rcu_rnn_t *out, int cell, int layers, int in_dim, int 
   plan_simt(h);
   h->in_l.resize(layers);
   h->wih.resize(layers);
+  h->wih_f32.resize(layers);
   h->gbias.resize(layers);
   h->host_bias.resize(layers);
   h->lw.resize((size_t)layers * h->D);
@@ -458,6 +460,19 @@ extern "C" int rnn_set_weights(rcu_rnn_t h, int layer, int dir, const float *W_i
       for (int k = 0; k < in; ++k) put(buf, (size_t)r * ldk + k, wih[(size_t)r * in + k]);
     CU(cudaMemcpy((char *)gw.p + (size_t)dir * nG * H * ldk * es, buf.data(), buf.size(),
                   cudaMemcpyHostToDevice));
+    if (bf) {  // fp32 of the rounded weights, for the backward pass's GEMMs
+      DevBuf &gf = h->wih_f32[layer];
+      const size_t gf_bytes = (size_t)D * nG * H * ldk * 4;
+      if (gf.n < gf_bytes) {
+        CU(gf.ensure(gf_bytes));
+        CU(cudaMemset(gf.p, 0, gf_bytes));
+      }
+      std::vector<float> fb((size_t)nG * H * ldk, 0.f);
+      for (int r = 0; r < nG * H; ++r)
+        for (int k = 0; k < in; ++k) fb[(size_t)r * ldk + k] = bf2f(f2bf(wih[(size_t)r * in + k]));
+      CU(cudaMemcpy((char *)gf.p + (size_t)dir * nG * H * ldk * 4, fb.data(), fb.size() * 4,
+                    cudaMemcpyHostToDevice));
+    }
   }
   // --- GEMM bias: LSTM b_ih + b_hh; GRU r,z: b_ih + b_hh, n: b_ih (b_hn stays with r*(.))
   {
@@ -538,16 +553,22 @@ extern "C" int rnn_set_weights(rcu_rnn_t h, int layer, int dir, const float *W_i
       for (int k = 0; k < H; ++k) hr[(size_t)q * ldH + k] = f2bf(whr[(size_t)q * H + k]);
     CU(lw.whr_bf.upload(hr.data(), hr.size() * 2));
   }
-  // --- plain fp32 copies for the backward pass
-  if (!bf) {
+  // --- plain fp32 copies for the backward pass (bf16 handles: of the rounded
+  //     weight matrices; biases stay fp32 as in the forward)
+  {
+    auto rw = [&](float v) { return bf ? bf2f(f2bf(v)) : v; };
     const int ldo = round_up(Hout, 8);
     std::vector<float> wp((size_t)nG * H * ldo, 0.f);
     for (int r = 0; r < nG * H; ++r)
-      for (int k = 0; k < Hout; ++k) wp[(size_t)r * ldo + k] = whh[(size_t)r * Hout + k];
+      for (int k = 0; k < Hout; ++k) wp[(size_t)r * ldo + k] = rw(whh[(size_t)r * Hout + k]);
     CU(lw.whh_plain.upload(wp.data(), wp.size() * 4));
     CU(lw.bih_plain.upload(bih.data(), (size_t)nG * H * 4));
     CU(lw.bhh_plain.upload(bhh.data(), (size_t)nG * H * 4));
-    if (P > 0) CU(lw.whr_plain.upload(whr.data(), (size_t)P * H * 4));
+    if (P > 0) {
+      std::vector<float> hr((size_t)P * H);
+      for (size_t q = 0; q < hr.size(); ++q) hr[q] = rw(whr[q]);
+      CU(lw.whr_plain.upload(hr.data(), hr.size() * 4));
+    }
   }
   lw.set = true;
   return RCU_OK;
@@ -776,7 +797,7 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
       h->end(s);
       h->used_tc_rec = true;
       // projection h_t = W_hr m_t for all steps and directions
-      float *Y = last ? y : h->ytmp;
+      float *Y = last ? y : (h->keep_out ? h->keep_out + (size_t)l * T * B * D * Hout : h->ytmp);
       h->begin("projection_gemm_tc", s);
       for (int d = 0; d < D; ++d) {
         e = launch_tc_gemm((const __nv_bfloat16 *)h->mbuf + (size_t)d * H, D * H,
@@ -794,7 +815,7 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
       }
       if (!last) {
         h->begin("convert_bf16", s);
-        CU(launch_convert<__nv_bfloat16>(h->ytmp, (__nv_bfloat16 *)h->ymid, (size_t)Mmax * D * P,
+        CU(launch_convert<__nv_bfloat16>(Y, (__nv_bfloat16 *)h->ymid, (size_t)Mmax * D * P,
                                          s));
         h->end(s);
       }
@@ -1020,8 +1041,8 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
   h->launches = 0;
   for (auto &w : h->lw)
     if (!w.set) return fail(RCU_ERR_STATE, "rnn_backward: weights missing for some layer/direction");
-  if (h->dtype != RCU_F32 || h->cclip || h->pclip)
-    return fail(RCU_ERR_UNSUPPORTED, "rnn_backward: fp32 networks without clipping");
+  if (h->cclip || h->pclip)
+    return fail(RCU_ERR_UNSUPPORTED, "rnn_backward: networks without clipping");
   if (T < 1 || B < 1 || !x || !dy) return fail(RCU_ERR_INVALID, "rnn_backward: need T, B >= 1, x and dy");
   if (h->cell == RCU_GRU && (c0 || dc_n || dc0))
     return fail(RCU_ERR_INVALID, "rnn_backward: c0/dc_n/dc0 are LSTM-only");
@@ -1092,7 +1113,9 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
                      float *dX) -> int {
     const int i = l * D + d, ldk = round_up(K, 8);
     const LayerDirW &lw = h->lw[(size_t)i];
-    const float *Wih = (const float *)h->wih[l].p + (size_t)d * G * ldk;
+    // fp32 W_ih (bf16 handles: of the rounded weights the forward used)
+    const float *Wih = (const float *)(h->dtype == RCU_BF16 ? h->wih_f32[l].p : h->wih[l].p) +
+                       (size_t)d * G * ldk;
     const float *dhnl = dh_n ? dh_n + (size_t)i * B * Ho : nullptr;
     // h_{t-1} for t = 0 .. T-1
     if (h0) CU(cudaMemcpyAsync(hp, h0 + (size_t)i * B * Ho, (size_t)B * Ho * 4, cudaMemcpyDeviceToDevice, s));

@@ -836,6 +836,45 @@ def test_backward_parity(spec):
     net.close()
 
 
+BWD_BF16_SPECS = [
+    wl.GRU_3L.scaled(T=8, B=130, in_dim=64, hidden=96, layers=2),      # tensor-core forward
+    wl.LSTM_T80.scaled(T=9, B=6, in_dim=24, hidden=40, dtype="bf16", h0_std=0.5, c0_std=0.5),
+    wl.LSTMP_2L.scaled(T=7, B=5, in_dim=24, hidden=64, proj=16),        # folded forward
+]
+
+
+@pytest.mark.parametrize("spec", BWD_BF16_SPECS, ids=lambda s: s.cell + f"-P{s.proj}")
+def test_backward_bf16_parity(spec):
+    """bf16 handles: the fp32 gradient of the model with the bf16-rounded
+    weights the forward used, against the oracle with the same rounded
+    weights (bf16 tier: relative 2e-2; the forward's bf16 activation
+    rounding is in the recomputed states)."""
+    inp = wl.make_rnn_inputs(spec, seed=13)
+    g = torch.Generator().manual_seed(98)
+    L, B, Ho = spec.layers, spec.B, spec.Hout
+    dy = torch.randn((spec.T, B, Ho), generator=g)
+    dev = torch.device("cuda")
+    net = binding.RNN.from_spec(spec)
+    net.set_weights(inp["weights"])
+
+    def d(t):
+        return None if t is None else t.to(dev)
+    dx, dh0, dc0, grads = net.backward(d(inp["x"]), d(dy), h0=d(inp["h0"]), c0=d(inp["c0"]))
+    torch.cuda.synchronize()
+    assert net.status() == 0
+    ref = oracle.rnn_backward(_cell(spec), inp["x"], inp["weights"], dy, hidden=spec.hidden,
+                              proj=spec.proj, h0=inp["h0"], c0=inp["c0"], bf16_weights=True)
+    pairs = [("dx", dx, ref["dx"]), ("dh0", dh0, ref["dh0"])]
+    for i in range(L):
+        for k in ("w_ih", "w_hh", "b_ih") + (("w_hr",) if spec.proj else ()):
+            pairs.append((f"d{k}[{i}]", grads[i][k], ref["d" + k][i]))
+    for name, got, want in pairs:
+        e = _rel(got.cpu().numpy().astype(np.float64), want)
+        print(f"{name}: rel {e:.2e}")
+        assert e <= BF16_REL, f"{name}: relative max error {e:.3e}"
+    net.close()
+
+
 def test_backward_errors():
     spec = BWD_SPECS[0]
     inp = wl.make_rnn_inputs(spec, seed=1)
@@ -845,12 +884,12 @@ def test_backward_errors():
     with pytest.raises(RuntimeError, match="no rnn_backward"):
         binding.rnn_get_weight_grads(net.h, 0, None, None, None, None)
     net.close()
-    for bad in (spec.scaled(dtype="bf16"),):
-        net = binding.RNN.from_spec(bad)
-        net.set_weights(wl.make_rnn_inputs(bad, seed=1)["weights"])
-        x = torch.zeros((bad.T, bad.B, bad.in_dim), device=dev)
-        dy = torch.zeros((bad.T, bad.B, bad.D * bad.Hout), device=dev)
-        with pytest.raises(RuntimeError, match="fp32 networks"):
-            binding.rnn_backward(net.h, bad.T, bad.B, x, None, None, dy, None, None, None, None,
-                                 None)
-        net.close()
+    net = binding.RNN.from_spec(spec)
+    net.set_weights(inp["weights"])
+    net.set_clip(binding.RCU_CLIP_CELL, (-1.0, 1.0))
+    x = torch.zeros((spec.T, spec.B, spec.in_dim), device=dev)
+    dy = torch.zeros((spec.T, spec.B, spec.Hout), device=dev)
+    with pytest.raises(RuntimeError, match="without clipping"):
+        binding.rnn_backward(net.h, spec.T, spec.B, x, None, None, dy, None, None, None, None,
+                             None)
+    net.close()
