@@ -65,7 +65,7 @@ def _load():
             lib.oracle_rssm_unroll2.argtypes = ([i, i, i, i, i, i] + [P] * 14 + [P, P, P, P, P, i, i]
                                                 + [i, P, P, P, P, P])
             lib.oracle_rnn_backward.restype = i
-            lib.oracle_rnn_backward.argtypes = [i] * 9 + [P] * 15 + [i]
+            lib.oracle_rnn_backward.argtypes = [i] * 9 + [P] * 16 + [i]
             lib.oracle_bf16_round.restype = ctypes.c_double
             lib.oracle_bf16_round.argtypes = [ctypes.c_float]
             lib.oracle_num_threads_default.restype = i
@@ -169,8 +169,8 @@ def rnn_forward(cell: int, x, weights, *, hidden: int, proj: int = 0, bidirectio
 
 
 def rnn_backward(cell: int, x, weights, dy, *, hidden: int, proj: int = 0,
-                 bidirectional: bool = False, h0=None, c0=None, dh_n=None, dc_n=None,
-                 bf16_weights: bool = False, threads: int = 0):
+                 bidirectional: bool = False, lengths=None, h0=None, c0=None, dh_n=None,
+                 dc_n=None, bf16_weights: bool = False, threads: int = 0):
     """Backward pass through time of a stacked LSTM / GRU, or LSTM with
     projection, optionally bidirectional (no lengths or clipping), in fp64:
     the gradients of a loss with dL/dy = dy [T,B,D*Ho] (and dL/dh_n
@@ -180,8 +180,10 @@ def rnn_backward(cell: int, x, weights, dy, *, hidden: int, proj: int = 0,
     zero) and w_hr (projection).  Returns a dict: dx [T,B,in], dh0
     [L*D,B,Ho], dc0 [L*D,B,H] (LSTM, else None), and lists over layer*D + dir
     of dw_ih, dw_hh, db_ih, db_hh, dw_hr (None without projection) in the
-    weights' shapes.  bf16_weights: the weight matrices are rounded to bf16
-    first (biases stay fp32), as in rnn_forward.
+    weights' shapes.  lengths: None or int32 [B] in [1, T]; row b runs its
+    first len_b steps as in rnn_forward and its dx is 0 beyond them.
+    bf16_weights: the weight matrices are rounded to bf16 first (biases stay
+    fp32), as in rnn_forward.
     """
     lib = _load()
     x = _f32(x)
@@ -201,6 +203,7 @@ def rnn_backward(cell: int, x, weights, dy, *, hidden: int, proj: int = 0,
         keep.extend(vals)
         arr[i] = _LayerW(*[_ptr(v) for v in vals])
     h0a, c0a, dya, dhn, dcn = _f32(h0), _f32(c0), _f32(dy), _f32(dh_n), _f32(dc_n)
+    ln = _i32(lengths)  # kept alive across the call
     in_l = [in_dim if i // D == 0 else D * Ho for i in range(LD)]
     dx = np.zeros((T, B, in_dim))
     dh0 = np.zeros((LD, B, Ho))
@@ -212,7 +215,7 @@ def rnn_backward(cell: int, x, weights, dy, *, hidden: int, proj: int = 0,
     dwhr = np.zeros(max(1, LD * proj * H))
     rc = lib.oracle_rnn_backward(int(cell), int(bidirectional), L, in_dim, H, int(proj),
                                  int(bool(bf16_weights)), T, B,
-                                 _ptr(x), _ptr(h0a), _ptr(c0a), ctypes.addressof(arr), _ptr(dya),
+                                 _ptr(x), _ptr(ln), _ptr(h0a), _ptr(c0a), ctypes.addressof(arr), _ptr(dya),
                                  _ptr(dhn), _ptr(dcn), _ptr(dx), _ptr(dh0), _ptr(dc0),
                                  _ptr(dwih), _ptr(dwhh), _ptr(dbih), _ptr(dbhh),
                                  _ptr(dwhr) if proj > 0 else None, int(threads))

@@ -511,10 +511,14 @@ int oracle_num_threads_default(void) {
 /* and steps; layouts follow the weights per (layer, direction) i = l*D + d */
 /* (dW_ih at offset sum_{j<i} nG*H*in_j, dW_hh at i*nG*H*Ho, db at i*nG*H,  */
 /* dW_hr at i*P*H).  Outputs: dx [T,B,in], dh0 [L*D,B,Ho], dc0 [L*D,B,H]    */
-/* (LSTM; may be NULL).  bf16_weights: the weight matrices are first rounded */
+/* (LSTM; may be NULL).  lengths: NULL or [B] in [1, T]: row b runs steps    */
+/* t < len_b as in the forward (the backward direction from len_b - 1), its */
+/* dh_n enters at its last processed step and dx is 0 at t >= len_b.        */
+/* bf16_weights: the weight matrices are first rounded                     */
 /* to bf16 (the forward oracle's convention; biases stay fp32).             */
 int oracle_rnn_backward(int cell, int bidir, int layers, int in_dim, int hidden, int proj,
-                        int bf16_weights, int T, int B, const float *x, const float *h0, const float *c0,
+                        int bf16_weights, int T, int B, const float *x, const int32_t *lengths,
+                        const float *h0, const float *c0,
                         const oracle_layer_w *w, const float *dy, const float *dh_n,
                         const float *dc_n, double *dx, double *dh0, double *dc0, double *dW_ih,
                         double *dW_hh, double *db_ih, double *db_hh, double *dW_hr,
@@ -522,6 +526,9 @@ int oracle_rnn_backward(int cell, int bidir, int layers, int in_dim, int hidden,
     if (cell != OR_LSTM && cell != OR_GRU) return -1;
     if (layers < 1 || in_dim < 1 || hidden < 1 || T < 1 || B < 1 || !x || !dy) return -1;
     if (proj < 0 || (proj > 0 && cell != OR_LSTM)) return -1;
+    if (lengths)
+        for (int b = 0; b < B; ++b)
+            if (lengths[b] < 1 || lengths[b] > T) return -1;
     const int D = bidir ? 2 : 1, LD = layers * D;
     const int H = hidden, P = proj, Ho = proj > 0 ? proj : hidden, DHo = D * Ho;
     const int nG = (cell == OR_LSTM) ? 4 : 3, G = nG * H;
@@ -587,6 +594,8 @@ int oracle_rnn_backward(int cell, int bidir, int layers, int in_dim, int hidden,
 #pragma omp for schedule(static)
 #endif
         for (int b = 0; b < B; ++b) {
+            /* row b runs steps t < len (the backward direction from t = len-1) */
+            const int len = lengths ? lengths[b] : T;
             /* ---- forward, keeping what the backward needs */
             for (int t = 0; t < T; ++t)
                 for (int k = 0; k < in_dim; ++k)
@@ -602,8 +611,8 @@ int oracle_rnn_backward(int cell, int bidir, int layers, int in_dim, int hidden,
                     for (int k = 0; k < Ho; ++k) hl[k] = h0 ? (double)h0[((size_t)i * B + b) * Ho + k] : 0.0;
                     for (int k = 0; k < H; ++k)
                         cl[k] = (lstm && c0) ? (double)c0[((size_t)i * B + b) * H + k] : 0.0;
-                    for (int s2 = 0; s2 < T; ++s2) {
-                        const int t = d == 0 ? s2 : T - 1 - s2;
+                    for (int s2 = 0; s2 < len; ++s2) {
+                        const int t = d == 0 ? s2 : len - 1 - s2;
                         const double *xt = Xl + (size_t)t * wmax, *hp = hl + (size_t)s2 * Ho;
                         double *hn_ = hl + (size_t)(s2 + 1) * Ho, *cn_ = cl + (size_t)(s2 + 1) * H;
                         double *mt = ml + (size_t)s2 * H;
@@ -664,8 +673,8 @@ int oracle_rnn_backward(int cell, int bidir, int layers, int in_dim, int hidden,
                     for (int k = 0; k < Ho; ++k) dhp[k] = dh_n ? (double)dh_n[((size_t)i * B + b) * Ho + k] : 0.0;
                     for (int k = 0; k < H; ++k)
                         dc[k] = (lstm && dc_n) ? (double)dc_n[((size_t)i * B + b) * H + k] : 0.0;
-                    for (int s2 = T - 1; s2 >= 0; --s2) {
-                        const int t = d == 0 ? s2 : T - 1 - s2;
+                    for (int s2 = len - 1; s2 >= 0; --s2) {
+                        const int t = d == 0 ? s2 : len - 1 - s2;
                         const double *g = gl + (size_t)s2 * (G + H);
                         const double *hp = hl + (size_t)s2 * Ho, *xt = Xl + (size_t)t * wmax;
                         const double *mt = ml + (size_t)s2 * H;

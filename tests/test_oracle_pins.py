@@ -960,3 +960,56 @@ def test_bptt_bf16_weights_is_fp32_bptt_of_rounded_weights():
         for u, v in zip(a[k], b[k]):
             assert np.array_equal(u, v), k
 
+
+
+@pytest.mark.parametrize("cell,bidir", [(oracle.LSTM, True), (oracle.GRU, False),
+                                        (oracle.LSTM, False)])
+def test_bptt_varlen_against_torch_autograd(cell, bidir):
+    """Variable lengths: the oracle's gradients equal torch float64 autograd
+    through pack_padded_sequence -> nn.LSTM / nn.GRU -> pad_packed_sequence
+    (h_n of each row at its own last step, zero gradient beyond it)."""
+    rng = np.random.default_rng(70 + cell + 2 * bidir)
+    T, B, in_dim, H, layers = 6, 4, 3, 5, 2
+    D = 2 if bidir else 1
+    ws = _rand_weights(rng, cell, layers, in_dim, H, D=D)
+    x = rng.standard_normal((T, B, in_dim)).astype(np.float32)
+    lengths = np.array([6, 2, 4, 4], np.int32)
+    h0 = (0.5 * rng.standard_normal((layers * D, B, H))).astype(np.float32)
+    dy = rng.standard_normal((T, B, D * H)).astype(np.float32)
+    dhn = rng.standard_normal((layers * D, B, H)).astype(np.float32)
+    lstm = cell == oracle.LSTM
+    g = oracle.rnn_backward(cell, x, ws, dy, hidden=H, bidirectional=bidir, lengths=lengths,
+                            h0=h0, dh_n=dhn)
+    kw = dict(input_size=in_dim, hidden_size=H, num_layers=layers, bidirectional=bidir,
+              dtype=torch.float64)
+    mod = torch.nn.LSTM(**kw) if lstm else torch.nn.GRU(**kw)
+    names = (("w_ih", "weight_ih"), ("w_hh", "weight_hh"), ("b_ih", "bias_ih"),
+             ("b_hh", "bias_hh"))
+    with torch.no_grad():
+        for layer in range(layers):
+            for d in range(D):
+                sfx = f"_l{layer}" + ("_reverse" if d else "")
+                for k, name in names:
+                    getattr(mod, name + sfx).copy_(torch.from_numpy(ws[layer * D + d][k]).double())
+    xt = torch.from_numpy(x).double().requires_grad_()
+    ht = torch.from_numpy(h0).double().requires_grad_()
+    packed = torch.nn.utils.rnn.pack_padded_sequence(xt, torch.from_numpy(lengths).long(),
+                                                     enforce_sorted=False)
+    state = (ht, torch.zeros_like(ht)) if lstm else ht
+    out, st = mod(packed, state)
+    y, _ = torch.nn.utils.rnn.pad_packed_sequence(out, total_length=T)
+    hn = st[0] if lstm else st
+    loss = (y * torch.from_numpy(dy).double()).sum() + (hn * torch.from_numpy(dhn).double()).sum()
+    loss.backward()
+    tol = dict(rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(g["dx"], xt.grad.numpy(), **tol)
+    np.testing.assert_allclose(g["dh0"], ht.grad.numpy(), **tol)
+    for layer in range(layers):
+        for d in range(D):
+            sfx = f"_l{layer}" + ("_reverse" if d else "")
+            for k, name in names:
+                np.testing.assert_allclose(g["d" + k][layer * D + d],
+                                           getattr(mod, name + sfx).grad.numpy(), **tol,
+                                           err_msg=f"d{k}{sfx}")
+    for b in range(B):
+        assert np.all(g["dx"][lengths[b]:, b] == 0.0)
