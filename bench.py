@@ -322,7 +322,7 @@ def make_train_runner(spec, inp, dev, net, d):
                       torch.empty((nG * H,), device=dev), torch.empty((nG * H,), device=dev)])
 
     def step():
-        binding.rnn_backward(net.h, T, B, d["x"], d["h0"], d["c0"], dy, None, None, dx, dh0, dc0)
+        binding.rnn_backward(net.h, T, B, d["x"], None, d["h0"], d["c0"], dy, None, None, dx, dh0, dc0)
         for layer in range(L):
             binding.rnn_get_weight_grads(net.h, layer, *grads[layer])
 

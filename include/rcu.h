@@ -199,25 +199,30 @@ RCU_API int rnn_forward_host(rcu_rnn_t h, int T, int B, const float *x, const in
  * Backward pass through time (BPTT), the training use of the unrolled cell
  * ("[Feature Request] CUDNN version of RSSM", pytorch/rl issue 366,
  * Motivation; "Integrating CuDNN API for LSTMs with projections",
- * pytorch/pytorch issue 46213, training discussion).  Handles without lengths
- * or clipping (else RCU_ERR_UNSUPPORTED): LSTM, GRU and LSTM with
- * projection, uni- or bidirectional; on an RCU_BF16 handle, the fp32
- * gradient of the model with the bf16-rounded weights its forward uses.  Given the forward's inputs x [T,B,in],
+ * pytorch/pytorch issue 46213, training discussion).  Handles without
+ * clipping (else RCU_ERR_UNSUPPORTED): LSTM, GRU and LSTM with projection,
+ * uni- or bidirectional, over padded or variable-length batches; on an
+ * RCU_BF16 handle, the fp32 gradient of the model with the bf16-rounded
+ * weights its forward uses.  Given the forward's inputs x [T,B,in], lengths
+ * (device int32 [B], each in [1, T], or NULL = all T; as rnn_forward),
  * h0 [L*D,B,Hout] / c0 [L*D,B,H] (or NULL) and the gradient of a loss with
  * respect to y, dy [T,B,D*Hout] (and to h_n / c_n, dh_n [L*D,B,Hout] / dc_n
  * [L*D,B,H] or NULL = 0), writes the gradients dx [T,B,in], dh0 [L*D,B,Hout]
  * and dc0 [L*D,B,H] (LSTM) — each may be NULL — and keeps the weight
  * gradients of every layer and direction, summed over rows and steps, for
- * rnn_get_weight_grads.  All
- * device pointers; asynchronous on `stream`; a device-side failure is
- * reported by rnn_get_status.
+ * rnn_get_weight_grads.  With lengths, row b's steps t >= lengths[b] take no
+ * part (as in a packed sequence): dy there is ignored, dx there is 0, h_n /
+ * c_n are the states at the row's last step (the reverse direction's at
+ * t = 0), and x there is not read.  All device pointers; asynchronous on
+ * `stream`; a device-side failure (a wait that ran out, an invalid length)
+ * is reported by rnn_get_status.
  * The forward is recomputed inside the call (every layer's output sequence
  * is kept), so only dh_{t-1} = W_hh^T dz_t runs step by step; the rest are
  * GEMMs over all T*B rows.
  */
-RCU_API int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const float *h0,
-                         const float *c0, const float *dy, const float *dh_n, const float *dc_n,
-                         float *dx, float *dh0, float *dc0, void *stream);
+RCU_API int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int32_t *lengths,
+                         const float *h0, const float *c0, const float *dy, const float *dh_n,
+                         const float *dc_n, float *dx, float *dh0, float *dc0, void *stream);
 /*
  * Weight gradients of layer `layer`, direction `dir` from the last rnn_backward, in the
  * weights' own layout: dW_ih [nG*H, in_l], dW_hh [nG*H, Hout], db_ih, db_hh

@@ -96,7 +96,7 @@ def load(path: Optional[str] = None):
             "rssm_set_actor": (I, [P, I, P, P, P, P, P]),
             "rssm_unroll_actor": (I, [P, I, I] + [P] * 8 + [P]),
             "rnn_forward_host": (I, [P, I, I] + [P] * 8),
-            "rnn_backward": (I, [P, I, I] + [P] * 10),
+            "rnn_backward": (I, [P, I, I] + [P] * 11),
             "rnn_get_weight_grads": (I, [P, I, I, P, P, P, P, P, P]),
             "rssm_unroll_host": (I, [P, I, I] + [P] * 8 + [P]),
             "rssm_unroll_actor_host": (I, [P, I, I] + [P] * 8 + [P]),
@@ -260,9 +260,10 @@ def rnn_forward_host(h, T: int, B: int, x, lengths, h0, c0, y, h_n, c_n, stream=
                                    _stream(stream)))
 
 
-def rnn_backward(h, T: int, B: int, x, h0, c0, dy, dh_n, dc_n, dx, dh0, dc0, stream=None):
+def rnn_backward(h, T: int, B: int, x, lengths, h0, c0, dy, dh_n, dc_n, dx, dh0, dc0,
+                 stream=None):
     """Backward pass through time (see rcu.h); device tensors."""
-    ins = [_dev(t) for t in (x, h0, c0, dy, dh_n, dc_n)]
+    ins = [_dev(x), _dev(lengths, torch.int32)] + [_dev(t) for t in (h0, c0, dy, dh_n, dc_n)]
     outs = [_dev(t) for t in (dx, dh0, dc0)]
     _check(load().rnn_backward(h, T, B, *[k[1] for k in ins], *[k[1] for k in outs],
                                _stream(stream)))
@@ -384,9 +385,9 @@ class RNN:
         rnn_forward(self.h, T, B, x, lengths, h0, c0, None, y, hn, cn, stream)
         return y, hn, cn
 
-    def backward(self, x, dy, h0=None, c0=None, dh_n=None, dc_n=None, stream=None):
+    def backward(self, x, dy, lengths=None, h0=None, c0=None, dh_n=None, dc_n=None, stream=None):
         """Gradients of a loss with dL/dy = dy (and dL/dh_n, dL/dc_n) through
-        the forward on x: returns (dx, dh0, dc0 or None, weight grads as a
+        the forward on x (with lengths: int32 [B] on the device): returns (dx, dh0, dc0 or None, weight grads as a
         list over layers of dicts w_ih, w_hh, b_ih, b_hh)."""
         T, B, in_dim = x.shape
         dev = x.device
@@ -394,7 +395,7 @@ class RNN:
         LD = self.layers * self.D
         dh0 = torch.empty((LD, B, self.Hout), device=dev)
         dc0 = torch.empty((LD, B, self.hidden), device=dev) if self.cell == "lstm" else None
-        rnn_backward(self.h, T, B, x, h0, c0, dy, dh_n, dc_n, dx, dh0, dc0, stream)
+        rnn_backward(self.h, T, B, x, lengths, h0, c0, dy, dh_n, dc_n, dx, dh0, dc0, stream)
         nG = 4 if self.cell == "lstm" else 3
         grads = []  # over layer * D + direction, like the weights
         for i in range(LD):

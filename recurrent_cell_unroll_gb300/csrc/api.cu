@@ -1034,8 +1034,8 @@ extern "C" int rnn_forward_host(rcu_rnn_t h, int T, int B, const float *x, const
 // so dm_t = W_hr^T dy_t + (W_hh W_hr)^T dz_{t+1}: the same kernel runs it with
 // W_hh W_hr in place of W_hh and A = dy W_hr (one GEMM, dh_n folded into the
 // last step) in place of dy; dh_t, dh0 and dW_hr follow from GEMMs.
-extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const float *h0,
-                            const float *c0, const float *dy, const float *dh_n,
+extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int32_t *lengths,
+                            const float *h0, const float *c0, const float *dy, const float *dh_n,
                             const float *dc_n, float *dx, float *dh0, float *dc0, void *stream) {
   if (!h) return fail(RCU_ERR_INVALID, "rnn_backward: NULL handle");
   h->launches = 0;
@@ -1077,7 +1077,10 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
                // bidirectional only: processing-order copies of one direction
                o_xr = take(D > 1 ? TBK : 0), o_yd = take(D > 1 ? TBO : 0),
                o_dyd = take(D > 1 ? TBO : 0), o_dxr = take(D > 1 ? TBK : 0),
-               o_tmp = take(D > 1 ? TBK : 0), o_ctl = take(64);
+               o_tmp = take(D > 1 ? TBK : 0),
+               // variable lengths: dy of one direction, zero past each row's end
+               o_dym = take(lengths ? TBO : 0),
+               o_xm = take(lengths ? (size_t)M * h->in_l[0] : 0), o_ctl = take(64);
   CU(h->bw.ensure(off * 4));
   float *wsf = (float *)h->bw.p;
   float *keep = wsf + o_keep, *hp = wsf + o_hp, *zin = wsf + o_zin, *zh = wsf + o_zh;
@@ -1090,14 +1093,18 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
   float *WhrT = wsf + o_whrt, *WhhT = wsf + o_whht, *Rw = wsf + o_r, *T5 = wsf + o_t5,
         *T6 = wsf + o_t6;
   float *XR = wsf + o_xr, *YD = wsf + o_yd, *DYD = wsf + o_dyd, *DXR = wsf + o_dxr,
-        *TMP = wsf + o_tmp;
+        *TMP = wsf + o_tmp, *DYM = wsf + o_dym, *XM = wsf + o_xm;
   unsigned *ctr = (unsigned *)(wsf + o_ctl);
   if ((int)h->gw.size() < L * D) h->gw.resize((size_t)L * D);
   h->grads_ready = false;
   int launches = 0;
-  // ---- forward again, keeping every layer's output sequence
+  // ---- forward again, keeping every layer's output sequence.  With variable
+  // lengths the forward writes no step past a row's end: those entries of the
+  // inner layers' outputs are zeroed first, and x is read through a copy zero
+  // there, so every operand past a row's end is 0 (its gradient terms vanish)
+  if (lengths && L > 1) CU(cudaMemsetAsync(keep, 0, (size_t)(L - 1) * TBY * 4, s));
   h->keep_out = keep;
-  int rc = rnn_forward(h, T, B, x, nullptr, h0, c0, nullptr, keep + (size_t)(L - 1) * TBY,
+  int rc = rnn_forward(h, T, B, x, lengths, h0, c0, nullptr, keep + (size_t)(L - 1) * TBY,
                        nullptr, nullptr, stream);
   h->keep_out = nullptr;
   if (rc != RCU_OK) return rc;
@@ -1117,6 +1124,17 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
     const float *Wih = (const float *)(h->dtype == RCU_BF16 ? h->wih_f32[l].p : h->wih[l].p) +
                        (size_t)d * G * ldk;
     const float *dhnl = dh_n ? dh_n + (size_t)i * B * Ho : nullptr;
+    // variable lengths: dy zero past each row's end, dh_n added at its last
+    // step (h_n is the state there); the recurrence then carries no dh_n
+    if (lengths) {
+      h->begin("bwd_mask", s);
+      cudaError_t e = launch_mask_steps(dYdir, Ho, T, B, lengths, dhnl, DYM, s);
+      h->end(s);
+      if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: mask: %s", cudaGetErrorString(e));
+      dYdir = DYM;
+      dhnl = nullptr;
+      ++launches;
+    }
     // h_{t-1} for t = 0 .. T-1
     if (h0) CU(cudaMemcpyAsync(hp, h0 + (size_t)i * B * Ho, (size_t)B * Ho * 4, cudaMemcpyDeviceToDevice, s));
     else CU(cudaMemsetAsync(hp, 0, (size_t)B * Ho * 4, s));
@@ -1164,6 +1182,7 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
     a.gates = zin; a.zh = zh; a.cs = cs; a.c0 = c0l; a.hp = hp; a.dy = rec_dy;
     a.dhn = P > 0 ? nullptr : dhnl;
     a.dcn = dc_n ? dc_n + (size_t)i * B * H : nullptr;
+    a.lengths = lengths;
     a.DA = DA; a.DR = DR;
     a.dh0 = (P > 0 || !dh0) ? nullptr : dh0 + (size_t)i * B * H;
     a.dc0 = dc0 ? dc0 + (size_t)i * B * H : nullptr;
@@ -1224,10 +1243,17 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
     return RCU_OK;
   };
 
+  if (lengths) {
+    h->begin("bwd_mask", s);
+    cudaError_t e = launch_mask_steps(x, h->in_l[0], T, B, lengths, nullptr, XM, s);
+    h->end(s);
+    if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: mask: %s", cudaGetErrorString(e));
+    ++launches;
+  }
   const float *dYcur = dy;
   for (int l = L - 1; l >= 0; --l) {
     const int K = h->in_l[l];
-    const float *Xl = l == 0 ? x : keep + (size_t)(l - 1) * TBY;
+    const float *Xl = l == 0 ? (lengths ? XM : x) : keep + (size_t)(l - 1) * TBY;
     const float *Yl = keep + (size_t)l * TBY;
     float *dXl = l == 0 ? dx : (dYcur == dYa ? dYb : dYa);
     if (l > 0 && !dXl) return fail(RCU_ERR_INVALID, "rnn_backward: internal");
@@ -1237,9 +1263,11 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
       for (int d = 0; d < 2; ++d) {
         // direction d's sequences in its processing order
         h->begin("bwd_reorder", s);
-        cudaError_t e = launch_gather_steps(Yl, DHo, d * Ho, Ho, T, B, d == 1, YD, s);
-        if (e == cudaSuccess) e = launch_gather_steps(dYcur, DHo, d * Ho, Ho, T, B, d == 1, DYD, s);
-        if (e == cudaSuccess && d == 1) e = launch_gather_steps(Xl, K, 0, K, T, B, true, XR, s);
+        cudaError_t e = launch_gather_steps(Yl, DHo, d * Ho, Ho, T, B, d == 1, lengths, YD, s);
+        if (e == cudaSuccess)
+          e = launch_gather_steps(dYcur, DHo, d * Ho, Ho, T, B, d == 1, lengths, DYD, s);
+        if (e == cudaSuccess && d == 1)
+          e = launch_gather_steps(Xl, K, 0, K, T, B, true, lengths, XR, s);
         h->end(s);
         if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: reorder: %s", cudaGetErrorString(e));
         launches += d == 1 ? 3 : 2;
@@ -1247,7 +1275,7 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const flo
         if (int r = run_dir(l, d, d == 1 ? XR : Xl, K, YD, DYD, dXd)) return r;
         if (d == 1 && dXl) {  // dX of the layer input: the forward one plus the reversed backward one
           h->begin("bwd_reorder", s);
-          e = launch_gather_steps(DXR, K, 0, K, T, B, true, TMP, s);
+          e = launch_gather_steps(DXR, K, 0, K, T, B, true, lengths, TMP, s);
           if (e == cudaSuccess) e = launch_add(dXl, TMP, (size_t)M * K, s);
           h->end(s);
           if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: reorder: %s", cudaGetErrorString(e));

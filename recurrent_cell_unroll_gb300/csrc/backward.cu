@@ -64,6 +64,10 @@ __global__ void bwd_prep_kernel(int T, int B, int H, int cell, float *__restrict
 
 constexpr int UMAX = 16;  // hidden units per CTA (register tile width)
 
+// a row length clamped to [1, T] (the forward flags out-of-range lengths in
+// the status word and runs them clamped the same way)
+__device__ __forceinline__ int clamp_len(int len, int T) { return len < 1 ? 1 : (len > T ? T : len); }
+
 // 16-byte asynchronous global -> shared copy (cached in L2 only)
 __device__ __forceinline__ void cp_async16(float *dst, const float *src) {
   const unsigned d = (unsigned)__cvta_generic_to_shared(dst);
@@ -88,6 +92,7 @@ struct BwdParams {
   const float *hp;    // GRU: [T*B][H] h_{t-1}
   const float *dy;    // [T*B][H]
   const float *dhn, *dcn;  // [B][H] or NULL
+  const int32_t *lengths;  // [B] or NULL: row b runs steps 0 .. len_b - 1 only
   float *DA, *DR;     // [T*B][G]: input-side and hidden-side gate gradients (LSTM: DR == DA)
   float *dh0, *dc0;   // [B][H] or NULL
   unsigned *ctr;
@@ -136,9 +141,19 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
       if (j >= nu) continue;
       const int u = u0 + j, b = b0 + bl;
       const size_t r = (size_t)t * B + b;
+      float *da = p.DA + r * G;
+      if (p.lengths && t >= clamp_len(p.lengths[b], p.T)) {
+        // a step past the row's end: no gate gradient, and the carried dh
+        // (zero: dh_n enters through dy at the row's last step) and dc pass
+        // through unchanged
+        float *dr = p.DR + r * G;
+        for (int q = 0; q < (lstm ? 4 : 3); ++q) da[q * H + u] = 0.f;
+        if (!lstm)
+          for (int q = 0; q < 3; ++q) dr[q * H + u] = 0.f;
+        continue;
+      }
       const float dh = p.dy[r * H + u] + dhrec[e];
       const float *g = p.gates + r * G;
-      float *da = p.DA + r * G;
       if (lstm) {
         const float i = g[u], f = g[H + u], gg = g[2 * H + u], o = g[3 * H + u];
         const float c = p.cs[r * H + u];
@@ -359,25 +374,60 @@ __global__ void add_kernel(float *__restrict__ dst, const float *__restrict__ sr
 namespace {
 // out[s][b][c] = in[t][b][col0 + c], t = reverse ? T-1-s : s (row stride ldi)
 __global__ void gather_steps_kernel(const float *__restrict__ in, int ldi, int col0, int w, int T,
-                                    int B, int reverse, float *__restrict__ out) {
+                                    int B, int reverse, const int32_t *__restrict__ lengths,
+                                    float *__restrict__ out) {
   const size_t n = (size_t)T * B * w;
   for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
        e += (size_t)gridDim.x * blockDim.x) {
     const int c = (int)(e % w);
     const size_t row = e / w;  // s * B + b
     const int sidx = (int)(row / B), b = (int)(row % B);
-    const int t = reverse ? T - 1 - sidx : sidx;
+    // reversal within each row's own length; steps past it stay in place
+    const int len = lengths ? clamp_len(lengths[b], T) : T;
+    const int t = (reverse && sidx < len) ? len - 1 - sidx : sidx;
     out[e] = in[((size_t)t * B + b) * ldi + col0 + c];
+  }
+}
+// out[t][b][:] = in[t][b][:] (+ dhn[b][:] at t = len_b - 1) for t < len_b, 0
+// past the row's end; out may equal in
+__global__ void mask_steps_kernel(const float *in, int w, int T, int B,
+                                  const int32_t *__restrict__ lengths,
+                                  const float *__restrict__ dhn, float *out) {
+  const size_t n = (size_t)T * B * w;
+  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (size_t)gridDim.x * blockDim.x) {
+    const int c = (int)(e % w);
+    const size_t row = e / w;
+    const int t = (int)(row / B), b = (int)(row % B);
+    const int len = clamp_len(lengths[b], T);
+    float v = 0.f;
+    if (t < len) {
+      v = in[e];
+      if (dhn && t == len - 1) v += dhn[(size_t)b * w + c];
+    }
+    out[e] = v;
   }
 }
 }  // namespace
 
 cudaError_t launch_gather_steps(const float *in, int ldi, int col0, int w, int T, int B,
-                                bool reverse, float *out, cudaStream_t s) {
+                                bool reverse, const int32_t *lengths, float *out,
+                                cudaStream_t s) {
   const size_t n = (size_t)T * B * w;
   if (n == 0) return cudaSuccess;
   const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, 65535u * 8);
-  gather_steps_kernel<<<blocks, 256, 0, s>>>(in, ldi, col0, w, T, B, reverse ? 1 : 0, out);
+  gather_steps_kernel<<<blocks, 256, 0, s>>>(in, ldi, col0, w, T, B, reverse ? 1 : 0, lengths,
+                                             out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mask_steps(const float *in, int w, int T, int B, const int32_t *lengths,
+                              const float *dhn, float *out, cudaStream_t s) {
+  const size_t n = (size_t)T * B * w;
+  if (n == 0) return cudaSuccess;
+  if (!lengths) return cudaErrorInvalidValue;
+  const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, 65535u * 8);
+  mask_steps_kernel<<<blocks, 256, 0, s>>>(in, w, T, B, lengths, dhn, out);
   return cudaGetLastError();
 }
 
@@ -399,7 +449,7 @@ cudaError_t launch_bwd_rec(const BwdRecArgs &a, int nsm, cudaStream_t s) {
   p.Gp = rp.Gp; p.KC = rp.KC; p.KS = rp.KS; p.BS = rp.BS; p.NUG = rp.NUG;
   p.Whh = a.Whh; p.ldw = a.ldw;
   p.gates = a.gates; p.zh = a.zh; p.cs = a.cs; p.c0 = a.c0; p.hp = a.hp;
-  p.dy = a.dy; p.dhn = a.dhn; p.dcn = a.dcn;
+  p.dy = a.dy; p.dhn = a.dhn; p.dcn = a.dcn; p.lengths = a.lengths;
   p.DA = a.DA; p.DR = a.DR; p.dh0 = a.dh0; p.dc0 = a.dc0;
   p.ctr = a.ctr; p.err = a.err; p.timeout_ns = a.timeout_ns; p.drop_arrival = a.drop_arrival;
   const size_t smem = rp.smem;

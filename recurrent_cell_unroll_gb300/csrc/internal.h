@@ -134,15 +134,25 @@ cudaError_t launch_bwd_prep(int T, int B, int H, int cell, float *zin, const flo
                             const float *c0, float *cs, float *ms, cudaStream_t s);
 // dst[i] += src[i], i < n
 cudaError_t launch_add(float *dst, const float *src, size_t n, cudaStream_t s);
-// out[s][b][0..w) = in[t][b][col0 .. col0+w) with t = s, or T-1-s when reversed
-// (in: row stride ldi per (t, b); out: contiguous [T][B][w])
+// out[s][b][0..w) = in[t][b][col0 .. col0+w) with t = s, or, reversed,
+// t = len_b-1-s for s < len_b and t = s past the row's end (len_b = T without
+// lengths); the map is its own inverse.  in: row stride ldi per (t, b);
+// out: contiguous [T][B][w]
 cudaError_t launch_gather_steps(const float *in, int ldi, int col0, int w, int T, int B,
-                                bool reverse, float *out, cudaStream_t s);
+                                bool reverse, const int32_t *lengths, float *out,
+                                cudaStream_t s);
+// out[t][b][:] = in[t][b][:] for t < len_b, plus dhn[b][:] (NULL: none) at
+// t = len_b - 1, and 0 for t >= len_b; [T][B][w] contiguous, out may be in
+cudaError_t launch_mask_steps(const float *in, int w, int T, int B, const int32_t *lengths,
+                              const float *dhn, float *out, cudaStream_t s);
 struct BwdRecArgs {
   int T, B, H, cell;
   const float *Whh;  // [nG*H][ldw]
   int ldw;
   const float *gates, *zh, *cs, *c0, *hp, *dy, *dhn, *dcn;
+  // [B] or NULL: steps t >= lengths[b] get zero gate gradients and pass the
+  // carried gradients through (dh_n must then come in through dy, dhn NULL)
+  const int32_t *lengths;
   float *DA, *DR, *dh0, *dc0;
   unsigned *ctr;  // zeroed before the launch
   int *err;

@@ -794,15 +794,31 @@ BWD_SPECS = [
     wl.LSTMP_2L.scaled(T=5, B=4, in_dim=8, hidden=16, proj=6, dtype="f32", bidir=True,
                        h0_std=0.5),
     wl.BILSTM_VAR.scaled(T=32, B=64, in_dim=256, hidden=256, varlen=None),
+    # variable lengths (length 1 and T both drawn)
+    wl.LSTM_T80.scaled(T=9, B=7, in_dim=12, hidden=20, layers=2, varlen=(1, 9), h0_std=0.5,
+                       c0_std=0.5),
+    wl.GRU_3L.scaled(T=8, B=9, in_dim=16, hidden=24, layers=2, dtype="f32", varlen=(1, 8),
+                     h0_std=0.3),
+    wl.BILSTM_VAR.scaled(T=10, B=6, in_dim=12, hidden=20, layers=2, varlen=(1, 10), h0_std=0.5,
+                         c0_std=0.5),
+    wl.GRU_3L.scaled(T=7, B=5, in_dim=9, hidden=11, layers=1, dtype="f32", bidir=True,
+                     varlen=(1, 7)),
+    wl.LSTMP_2L.scaled(T=7, B=5, in_dim=8, hidden=16, proj=6, dtype="f32", bidir=True,
+                       varlen=(1, 7), h0_std=0.5),
+    wl.BILSTM_VAR.scaled(T=40, B=64, in_dim=256, hidden=256, varlen=(5, 40)),
 ]
+
+
+def _bwd_id(s):
+    return (f"{s.cell}-L{s.layers}-D{s.D}-T{s.T}-B{s.B}-H{s.hidden}-P{s.proj}"
+            + ("-varlen" if s.varlen else ""))
 
 
 def _rel(a, b):
     return float(np.abs(a - b).max() / max(np.abs(b).max(), 1e-30))
 
 
-@pytest.mark.parametrize("spec", BWD_SPECS,
-                         ids=lambda s: f"{s.cell}-L{s.layers}-D{s.D}-T{s.T}-B{s.B}-H{s.hidden}-P{s.proj}")
+@pytest.mark.parametrize("spec", BWD_SPECS, ids=_bwd_id)
 def test_backward_parity(spec):
     inp = wl.make_rnn_inputs(spec, seed=12)
     g = torch.Generator().manual_seed(99)
@@ -816,13 +832,19 @@ def test_backward_parity(spec):
 
     def d(t):
         return None if t is None else t.to(dev)
-    dx, dh0, dc0, grads = net.backward(d(inp["x"]), d(dy), h0=d(inp["h0"]), c0=d(inp["c0"]),
-                                       dh_n=d(dhn), dc_n=d(dcn))
+    dx, dh0, dc0, grads = net.backward(d(inp["x"]), d(dy), lengths=d(inp["lengths"]),
+                                       h0=d(inp["h0"]), c0=d(inp["c0"]), dh_n=d(dhn),
+                                       dc_n=d(dcn))
     torch.cuda.synchronize()
     assert net.status() == 0
     ref = oracle.rnn_backward(_cell(spec), inp["x"], inp["weights"], dy, hidden=H,
-                              proj=spec.proj, bidirectional=spec.bidir, h0=inp["h0"],
-                              c0=inp["c0"], dh_n=dhn, dc_n=dcn)
+                              proj=spec.proj, bidirectional=spec.bidir,
+                              lengths=inp["lengths"], h0=inp["h0"], c0=inp["c0"], dh_n=dhn,
+                              dc_n=dcn)
+    if inp["lengths"] is not None:  # no gradient reaches x past a row's end
+        dxc = dx.cpu().numpy()
+        for b, n in enumerate(inp["lengths"].tolist()):
+            assert np.all(dxc[n:, b] == 0.0)
     pairs = [("dx", dx, ref["dx"]), ("dh0", dh0, ref["dh0"])]
     if spec.cell == "lstm":
         pairs.append(("dc0", dc0, ref["dc0"]))
@@ -840,10 +862,11 @@ BWD_BF16_SPECS = [
     wl.GRU_3L.scaled(T=8, B=130, in_dim=64, hidden=96, layers=2),      # tensor-core forward
     wl.LSTM_T80.scaled(T=9, B=6, in_dim=24, hidden=40, dtype="bf16", h0_std=0.5, c0_std=0.5),
     wl.LSTMP_2L.scaled(T=7, B=5, in_dim=24, hidden=64, proj=16),        # folded forward
+    wl.LSTM_T80.scaled(T=9, B=6, in_dim=24, hidden=40, dtype="bf16", varlen=(1, 9)),
 ]
 
 
-@pytest.mark.parametrize("spec", BWD_BF16_SPECS, ids=lambda s: s.cell + f"-P{s.proj}")
+@pytest.mark.parametrize("spec", BWD_BF16_SPECS, ids=_bwd_id)
 def test_backward_bf16_parity(spec):
     """bf16 handles: the fp32 gradient of the model with the bf16-rounded
     weights the forward used, against the oracle with the same rounded
@@ -859,11 +882,13 @@ def test_backward_bf16_parity(spec):
 
     def d(t):
         return None if t is None else t.to(dev)
-    dx, dh0, dc0, grads = net.backward(d(inp["x"]), d(dy), h0=d(inp["h0"]), c0=d(inp["c0"]))
+    dx, dh0, dc0, grads = net.backward(d(inp["x"]), d(dy), lengths=d(inp["lengths"]),
+                                       h0=d(inp["h0"]), c0=d(inp["c0"]))
     torch.cuda.synchronize()
     assert net.status() == 0
     ref = oracle.rnn_backward(_cell(spec), inp["x"], inp["weights"], dy, hidden=spec.hidden,
-                              proj=spec.proj, h0=inp["h0"], c0=inp["c0"], bf16_weights=True)
+                              proj=spec.proj, lengths=inp["lengths"], h0=inp["h0"],
+                              c0=inp["c0"], bf16_weights=True)
     pairs = [("dx", dx, ref["dx"]), ("dh0", dh0, ref["dh0"])]
     for i in range(L):
         for k in ("w_ih", "w_hh", "b_ih") + (("w_hr",) if spec.proj else ()):
@@ -890,6 +915,6 @@ def test_backward_errors():
     x = torch.zeros((spec.T, spec.B, spec.in_dim), device=dev)
     dy = torch.zeros((spec.T, spec.B, spec.Hout), device=dev)
     with pytest.raises(RuntimeError, match="without clipping"):
-        binding.rnn_backward(net.h, spec.T, spec.B, x, None, None, dy, None, None, None, None,
+        binding.rnn_backward(net.h, spec.T, spec.B, x, None, None, None, dy, None, None, None, None,
                              None)
     net.close()
