@@ -66,6 +66,8 @@ def _load():
                                                 + [i, P, P, P, P, P])
             lib.oracle_rnn_backward.restype = i
             lib.oracle_rnn_backward.argtypes = [i] * 9 + [P] * 16 + [i]
+            lib.oracle_rssm_backward.restype = i
+            lib.oracle_rssm_backward.argtypes = [i] * 6 + [P] * 31
             lib.oracle_bf16_round.restype = ctypes.c_double
             lib.oracle_bf16_round.argtypes = [ctypes.c_float]
             lib.oracle_num_threads_default.restype = i
@@ -172,7 +174,8 @@ def rnn_backward(cell: int, x, weights, dy, *, hidden: int, proj: int = 0,
                  bidirectional: bool = False, lengths=None, h0=None, c0=None, dh_n=None,
                  dc_n=None, bf16_weights: bool = False, threads: int = 0):
     """Backward pass through time of a stacked LSTM / GRU, or LSTM with
-    projection, optionally bidirectional (no lengths or clipping), in fp64:
+    projection, optionally bidirectional, over padded or variable-length
+    batches (no clipping), in fp64:
     the gradients of a loss with dL/dy = dy [T,B,D*Ho] (and dL/dh_n
     [L*D,B,Ho], dL/dc_n [L*D,B,H], None = 0; Ho = proj or hidden).
 
@@ -259,6 +262,44 @@ def rssm_unroll(weights, actions, eps, *, state0=None, belief0=None, rows=None, 
     if rc != 0:
         raise ValueError("oracle_rssm_unroll: invalid arguments")
     return means, stds, states, beliefs
+
+
+RSSM_WEIGHTS = ("W1", "b1", "W_ih", "W_hh", "b_ih", "b_hh", "W2", "b2", "W3", "b3")
+
+
+def rssm_backward(weights, actions, eps, *, state0=None, belief0=None, dmeans=None, dstds=None,
+                  dstates=None, dbeliefs=None):
+    """Backward pass through time of the RSSM prior unroll with given actions
+    (rssm_unroll), in fp64: the gradients of a loss whose gradient with
+    respect to the outputs is dmeans, dstds, dstates [T,B,S] and dbeliefs
+    [T,B,RH] (None = 0).  Returns a dict: dstate0 [B,S], dbelief0 [B,RH],
+    dactions [T,B,A] and d<name> for every weight and bias of rssm_unroll's
+    dict, in its shape.  eps is an input (the noise), not differentiated.
+    """
+    lib = _load()
+    a = _f32(actions)
+    e = _f32(eps)
+    T, B, S = e.shape
+    A = a.shape[2] if a is not None else 0
+    W = {k: _f32(weights.get(k)) for k in RSSM_WEIGHTS}
+    Hd = W["W1"].shape[0]
+    RH = W["W_hh"].shape[1]
+    s0, b0 = _f32(state0), _f32(belief0)
+    g_in = [_f32(v) for v in (dmeans, dstds, dstates, dbeliefs)]
+    shapes = {"W1": (Hd, S + A), "b1": (Hd,), "W_ih": (3 * RH, Hd), "W_hh": (3 * RH, RH),
+              "b_ih": (3 * RH,), "b_hh": (3 * RH,), "W2": (Hd, RH), "b2": (Hd,),
+              "W3": (2 * S, Hd), "b3": (2 * S,)}
+    out = {"dstate0": np.zeros((B, S)), "dbelief0": np.zeros((B, RH)),
+           "dactions": np.zeros((T, B, A))}
+    for k in RSSM_WEIGHTS:
+        out["d" + k] = np.zeros(shapes[k])
+    rc = lib.oracle_rssm_backward(
+        S, A, Hd, RH, T, B, *[_ptr(W[k]) for k in RSSM_WEIGHTS], _ptr(s0), _ptr(b0), _ptr(a),
+        _ptr(e), *[_ptr(v) for v in g_in], _ptr(out["dstate0"]), _ptr(out["dbelief0"]),
+        _ptr(out["dactions"]), *[_ptr(out["d" + k]) for k in RSSM_WEIGHTS])
+    if rc != 0:
+        raise ValueError("oracle_rssm_backward: invalid arguments")
+    return out
 
 
 def rssm_unroll_actor(weights, actor, eps, *, state0=None, belief0=None, rows=None,

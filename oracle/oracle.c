@@ -774,3 +774,212 @@ int oracle_rnn_backward(int cell, int bidir, int layers, int in_dim, int hidden,
     free(Wih); free(Whh); free(bih); free(bhh); free(Whr); free(off_ih);
     return 0;
 }
+
+/* ---------------------------------------------------------------------- */
+/* Backward pass through time of the RSSM prior unroll with given actions   */
+/* (the training use of the unroll named in "[Feature Request] CUDNN version */
+/* of RSSM", pytorch/rl issue 366, Motivation; the forward is the same       */
+/* issue's Solution, as in oracle_rssm_unroll2 above).                       */
+/*                                                                          */
+/* Given the gradient of a loss with respect to every output of the unroll  */
+/* (dmeans, dstds, dstates [T,B,S], dbeliefs [T,B,RH]; any may be NULL =    */
+/* 0), returns the gradient with respect to state0 [B,S], belief0 [B,RH],   */
+/* the actions [T,B,A] and every weight and bias (summed over rows and      */
+/* steps, the weights' own layouts).  The noise eps is an input, not a      */
+/* parameter.  One step of the prior, per row, is                            */
+/*   u = W1 [s_{t-1}, a_t] + b1,  x = ELU(u)                                 */
+/*   h_t = GRUCell(x, h_{t-1})    (r, z, n gates; reset after W_hn h)       */
+/*   v = W2 h_t + b2,  q = ELU(v),  p = W3 q + b3                            */
+/*   mean = p[0:S],  std = softplus(p[S:2S]) + 0.1,  s_t = mean + eps * std */
+/* and the chain rule through these, taken in reverse time, is written out  */
+/* term by term below.  Rows are processed one after another (the weight   */
+/* gradients sum over all of them).                                          */
+/* ---------------------------------------------------------------------- */
+static double elu_grad(double u) { return u > 0.0 ? 1.0 : exp(u); }
+
+int oracle_rssm_backward(int S, int A, int Hd, int RH, int T, int B, const float *W1,
+                         const float *b1, const float *Wih, const float *Whh, const float *bih,
+                         const float *bhh, const float *W2, const float *b2, const float *W3,
+                         const float *b3, const float *state0, const float *belief0,
+                         const float *actions, const float *eps, const float *dmeans,
+                         const float *dstds, const float *dstates, const float *dbeliefs,
+                         double *dstate0, double *dbelief0, double *dactions, double *dW1,
+                         double *db1, double *dWih, double *dWhh, double *dbih, double *dbhh,
+                         double *dW2, double *db2, double *dW3, double *db3) {
+    if (S < 1 || A < 0 || Hd < 1 || RH < 1 || T < 0 || B < 0) return -1;
+    if ((A > 0 && !actions) || !eps) return -1;
+    const int SA = S + A, G = 3 * RH;
+    double *w1 = widen(W1, (size_t)Hd * SA, 0), *vb1 = widen(b1, Hd, 0);
+    double *wih = widen(Wih, (size_t)G * Hd, 0), *whh = widen(Whh, (size_t)G * RH, 0);
+    double *vbih = widen(bih, G, 0), *vbhh = widen(bhh, G, 0);
+    double *w2 = widen(W2, (size_t)Hd * RH, 0), *vb2 = widen(b2, Hd, 0);
+    double *w3 = widen(W3, (size_t)2 * S * Hd, 0), *vb3 = widen(b3, (size_t)2 * S, 0);
+    memset(dW1, 0, (size_t)Hd * SA * sizeof(double));
+    memset(db1, 0, (size_t)Hd * sizeof(double));
+    memset(dWih, 0, (size_t)G * Hd * sizeof(double));
+    memset(dWhh, 0, (size_t)G * RH * sizeof(double));
+    memset(dbih, 0, (size_t)G * sizeof(double));
+    memset(dbhh, 0, (size_t)G * sizeof(double));
+    memset(dW2, 0, (size_t)Hd * RH * sizeof(double));
+    memset(db2, 0, (size_t)Hd * sizeof(double));
+    memset(dW3, 0, (size_t)2 * S * Hd * sizeof(double));
+    memset(db3, 0, (size_t)2 * S * sizeof(double));
+    /* per-step values of one row, kept by the forward for the reverse sweep */
+    const size_t Tn = T > 0 ? (size_t)T : 1;
+    double *in_s = (double *)calloc(Tn * SA, sizeof(double));   /* [s_{t-1}, a_t] */
+    double *u_s = (double *)calloc(Tn * Hd, sizeof(double));
+    double *x_s = (double *)calloc(Tn * Hd, sizeof(double));
+    double *hp_s = (double *)calloc(Tn * RH, sizeof(double));   /* h_{t-1} */
+    double *g_s = (double *)calloc(Tn * G, sizeof(double));     /* r, z, n */
+    double *hn_s = (double *)calloc(Tn * RH, sizeof(double));   /* W_hn h_{t-1} + b_hn */
+    double *h_s = (double *)calloc(Tn * RH, sizeof(double));
+    double *v_s = (double *)calloc(Tn * Hd, sizeof(double));
+    double *q_s = (double *)calloc(Tn * Hd, sizeof(double));
+    double *p_s = (double *)calloc(Tn * 2 * S, sizeof(double));
+    double *gs = (double *)calloc((size_t)S, sizeof(double));    /* dL/ds_t from step t+1 */
+    double *gh = (double *)calloc((size_t)RH, sizeof(double));   /* dL/dh_t from step t+1 */
+    double *ngs = (double *)calloc((size_t)S, sizeof(double));
+    double *ngh = (double *)calloc((size_t)RH, sizeof(double));
+    double *dp = (double *)calloc((size_t)2 * S, sizeof(double));
+    double *dv = (double *)calloc((size_t)Hd, sizeof(double));
+    double *dh = (double *)calloc((size_t)RH, sizeof(double));
+    double *din = (double *)calloc((size_t)G, sizeof(double));  /* input-side pre-activations */
+    double *dhid = (double *)calloc((size_t)G, sizeof(double)); /* hidden-side */
+    double *du = (double *)calloc((size_t)Hd, sizeof(double));
+    double *st = (double *)calloc((size_t)S, sizeof(double));
+    double *bel = (double *)calloc((size_t)RH, sizeof(double));
+    for (int b = 0; b < B; ++b) {
+        /* forward of row b */
+        for (int j = 0; j < S; ++j) st[j] = state0 ? (double)state0[(size_t)b * S + j] : 0.0;
+        for (int j = 0; j < RH; ++j) bel[j] = belief0 ? (double)belief0[(size_t)b * RH + j] : 0.0;
+        for (int t = 0; t < T; ++t) {
+            double *in = in_s + (size_t)t * SA;
+            for (int j = 0; j < S; ++j) in[j] = st[j];
+            for (int j = 0; j < A; ++j) in[S + j] = (double)actions[((size_t)t * B + b) * A + j];
+            for (int i = 0; i < Hd; ++i) {
+                double u = vb1 ? vb1[i] : 0.0;
+                for (int j = 0; j < SA; ++j) u += w1[(size_t)i * SA + j] * in[j];
+                u_s[(size_t)t * Hd + i] = u;
+                x_s[(size_t)t * Hd + i] = elu(u);
+            }
+            const double *x = x_s + (size_t)t * Hd;
+            memcpy(hp_s + (size_t)t * RH, bel, (size_t)RH * sizeof(double));
+            for (int j = 0; j < RH; ++j) {
+                double gi[3], gh3[3];
+                for (int q = 0; q < 3; ++q) {
+                    const int row = q * RH + j;
+                    gi[q] = vbih ? vbih[row] : 0.0;
+                    gh3[q] = vbhh ? vbhh[row] : 0.0;
+                    for (int k = 0; k < Hd; ++k) gi[q] += wih[(size_t)row * Hd + k] * x[k];
+                    for (int k = 0; k < RH; ++k) gh3[q] += whh[(size_t)row * RH + k] * bel[k];
+                }
+                const double r = sigmoid(gi[0] + gh3[0]), z = sigmoid(gi[1] + gh3[1]);
+                const double n = tanh(gi[2] + r * gh3[2]);
+                double *g = g_s + (size_t)t * G;
+                g[j] = r; g[RH + j] = z; g[2 * RH + j] = n;
+                hn_s[(size_t)t * RH + j] = gh3[2];
+                h_s[(size_t)t * RH + j] = (1.0 - z) * n + z * bel[j];
+            }
+            memcpy(bel, h_s + (size_t)t * RH, (size_t)RH * sizeof(double));
+            for (int i = 0; i < Hd; ++i) {
+                double v = vb2 ? vb2[i] : 0.0;
+                for (int k = 0; k < RH; ++k) v += w2[(size_t)i * RH + k] * bel[k];
+                v_s[(size_t)t * Hd + i] = v;
+                q_s[(size_t)t * Hd + i] = elu(v);
+            }
+            for (int i = 0; i < 2 * S; ++i) {
+                double v = vb3 ? vb3[i] : 0.0;
+                for (int k = 0; k < Hd; ++k) v += w3[(size_t)i * Hd + k] * q_s[(size_t)t * Hd + k];
+                p_s[(size_t)t * 2 * S + i] = v;
+            }
+            for (int j = 0; j < S; ++j) {
+                const double *p = p_s + (size_t)t * 2 * S;
+                st[j] = p[j] + (double)eps[((size_t)t * B + b) * S + j] * (softplus(p[S + j]) + 0.1);
+            }
+        }
+        /* reverse sweep of row b */
+        memset(gs, 0, (size_t)S * sizeof(double));
+        memset(gh, 0, (size_t)RH * sizeof(double));
+        for (int t = T - 1; t >= 0; --t) {
+            const size_t o = (size_t)t * B + b;
+            const double *p = p_s + (size_t)t * 2 * S;
+            /* sample: s = mean + eps * (softplus(p_S) + 0.1) */
+            for (int j = 0; j < S; ++j) {
+                const double ds = (dstates ? (double)dstates[o * S + j] : 0.0) + gs[j];
+                const double dmean = (dmeans ? (double)dmeans[o * S + j] : 0.0) + ds;
+                const double dsd = (dstds ? (double)dstds[o * S + j] : 0.0) +
+                                   ds * (double)eps[o * S + j];
+                dp[j] = dmean;
+                dp[S + j] = dsd * sigmoid(p[S + j]);  /* d softplus / dp */
+            }
+            /* head: p = W3 q + b3, q = ELU(v), v = W2 h + b2 */
+            const double *q = q_s + (size_t)t * Hd, *h = h_s + (size_t)t * RH;
+            for (int i = 0; i < 2 * S; ++i) {
+                db3[i] += dp[i];
+                for (int k = 0; k < Hd; ++k) dW3[(size_t)i * Hd + k] += dp[i] * q[k];
+            }
+            for (int k = 0; k < Hd; ++k) {
+                double dq = 0.0;
+                for (int i = 0; i < 2 * S; ++i) dq += w3[(size_t)i * Hd + k] * dp[i];
+                dv[k] = dq * elu_grad(v_s[(size_t)t * Hd + k]);
+            }
+            for (int i = 0; i < Hd; ++i) {
+                db2[i] += dv[i];
+                for (int k = 0; k < RH; ++k) dW2[(size_t)i * RH + k] += dv[i] * h[k];
+            }
+            for (int k = 0; k < RH; ++k) {
+                double a = (dbeliefs ? (double)dbeliefs[o * RH + k] : 0.0) + gh[k];
+                for (int i = 0; i < Hd; ++i) a += w2[(size_t)i * RH + k] * dv[i];
+                dh[k] = a;
+            }
+            /* GRU cell: h = (1 - z) n + z h_prev, n = tanh(i_n + r * hn) */
+            const double *g = g_s + (size_t)t * G, *hp = hp_s + (size_t)t * RH;
+            for (int j = 0; j < RH; ++j) {
+                const double r = g[j], z = g[RH + j], n = g[2 * RH + j];
+                const double dn = dh[j] * (1.0 - z), dz = dh[j] * (hp[j] - n);
+                const double dan = dn * (1.0 - n * n);
+                const double dar = dan * hn_s[(size_t)t * RH + j] * r * (1.0 - r);
+                const double daz = dz * z * (1.0 - z);
+                din[j] = dar; din[RH + j] = daz; din[2 * RH + j] = dan;
+                dhid[j] = dar; dhid[RH + j] = daz; dhid[2 * RH + j] = dan * r;
+                ngh[j] = dh[j] * z;
+            }
+            const double *x = x_s + (size_t)t * Hd;
+            for (int row = 0; row < G; ++row) {
+                dbih[row] += din[row];
+                dbhh[row] += dhid[row];
+                for (int k = 0; k < Hd; ++k) dWih[(size_t)row * Hd + k] += din[row] * x[k];
+                for (int k = 0; k < RH; ++k) dWhh[(size_t)row * RH + k] += dhid[row] * hp[k];
+            }
+            for (int k = 0; k < RH; ++k)
+                for (int row = 0; row < G; ++row) ngh[k] += whh[(size_t)row * RH + k] * dhid[row];
+            /* input MLP: x = ELU(u), u = W1 [s_{t-1}, a_t] + b1 */
+            for (int k = 0; k < Hd; ++k) {
+                double dx = 0.0;
+                for (int row = 0; row < G; ++row) dx += wih[(size_t)row * Hd + k] * din[row];
+                du[k] = dx * elu_grad(u_s[(size_t)t * Hd + k]);
+            }
+            const double *in = in_s + (size_t)t * SA;
+            for (int i = 0; i < Hd; ++i) {
+                db1[i] += du[i];
+                for (int j = 0; j < SA; ++j) dW1[(size_t)i * SA + j] += du[i] * in[j];
+            }
+            for (int j = 0; j < SA; ++j) {
+                double a = 0.0;
+                for (int i = 0; i < Hd; ++i) a += w1[(size_t)i * SA + j] * du[i];
+                if (j < S) ngs[j] = a;
+                else if (dactions) dactions[o * A + (j - S)] = a;
+            }
+            memcpy(gs, ngs, (size_t)S * sizeof(double));
+            memcpy(gh, ngh, (size_t)RH * sizeof(double));
+        }
+        if (dstate0) memcpy(dstate0 + (size_t)b * S, gs, (size_t)S * sizeof(double));
+        if (dbelief0) memcpy(dbelief0 + (size_t)b * RH, gh, (size_t)RH * sizeof(double));
+    }
+    free(in_s); free(u_s); free(x_s); free(hp_s); free(g_s); free(hn_s); free(h_s);
+    free(v_s); free(q_s); free(p_s); free(gs); free(gh); free(ngs); free(ngh); free(dp);
+    free(dv); free(dh); free(din); free(dhid); free(du); free(st); free(bel);
+    free(w1); free(vb1); free(wih); free(whh); free(vbih); free(vbhh);
+    free(w2); free(vb2); free(w3); free(vb3);
+    return 0;
+}

@@ -1013,3 +1013,106 @@ def test_bptt_varlen_against_torch_autograd(cell, bidir):
                                            err_msg=f"d{k}{sfx}")
     for b in range(B):
         assert np.all(g["dx"][lengths[b]:, b] == 0.0)
+
+
+# --------------------------------------------------------------------------- RSSM backward
+
+def _rssm_case(seed, T=5, B=3, S=4, A=3, Hd=6, RH=5):
+    spec = wl.RSSM_B50.scaled(T=T, B=B, state_dim=S, action_dim=A, hidden=Hd, rnn_hidden=RH,
+                              state0_std=1.0, belief0_std=0.5)
+    inp = wl.make_rssm_inputs(spec, seed=seed)
+    w = {k: v.numpy() for k, v in inp["weights"].items()}
+    rng = np.random.default_rng(seed)
+    grads = {k: rng.standard_normal((T, B, n)).astype(np.float32)
+             for k, n in (("dmeans", S), ("dstds", S), ("dstates", S), ("dbeliefs", RH))}
+    return w, inp["actions"].numpy(), inp["eps"].numpy(), inp["state0"].numpy(), \
+        inp["belief0"].numpy(), grads
+
+
+def test_rssm_backward_against_torch_autograd():
+    """The oracle's RSSM gradients equal torch float64 autograd through the
+    prior step assembled from nn.Linear / nn.GRUCell / ELU / softplus modules,
+    for every input and parameter."""
+    w, actions, eps, s0, b0, gr = _rssm_case(41)
+    T, B, A = actions.shape
+    S = eps.shape[2]
+    Hd, RH = w["W1"].shape[0], w["W_hh"].shape[1]
+    g = oracle.rssm_backward(w, actions, eps, state0=s0, belief0=b0, **gr)
+    d = lambda a: torch.from_numpy(np.asarray(a)).double()
+    lin1 = torch.nn.Linear(S + A, Hd, dtype=torch.float64)
+    gru = torch.nn.GRUCell(Hd, RH, dtype=torch.float64)
+    lin2 = torch.nn.Linear(RH, Hd, dtype=torch.float64)
+    lin3 = torch.nn.Linear(Hd, 2 * S, dtype=torch.float64)
+    params = {"W1": lin1.weight, "b1": lin1.bias, "W_ih": gru.weight_ih, "W_hh": gru.weight_hh,
+              "b_ih": gru.bias_ih, "b_hh": gru.bias_hh, "W2": lin2.weight, "b2": lin2.bias,
+              "W3": lin3.weight, "b3": lin3.bias}
+    with torch.no_grad():
+        for k, prm in params.items():
+            prm.copy_(d(w[k]))
+    st0, bl0, act = d(s0).requires_grad_(), d(b0).requires_grad_(), d(actions).requires_grad_()
+    state, belief = st0, bl0
+    loss = torch.zeros((), dtype=torch.float64)
+    for t in range(T):
+        x = torch.nn.functional.elu(lin1(torch.cat([state, act[t]], dim=-1)))
+        belief = gru(x, belief)
+        p = lin3(torch.nn.functional.elu(lin2(belief)))
+        mean = p[:, :S]
+        std = torch.nn.functional.softplus(p[:, S:]) + 0.1
+        state = mean + d(eps[t]) * std
+        loss = loss + (mean * d(gr["dmeans"][t])).sum() + (std * d(gr["dstds"][t])).sum() \
+            + (state * d(gr["dstates"][t])).sum() + (belief * d(gr["dbeliefs"][t])).sum()
+    loss.backward()
+    tol = dict(rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(g["dstate0"], st0.grad.numpy(), **tol)
+    np.testing.assert_allclose(g["dbelief0"], bl0.grad.numpy(), **tol)
+    np.testing.assert_allclose(g["dactions"], act.grad.numpy(), **tol)
+    for k, prm in params.items():
+        np.testing.assert_allclose(g["d" + k], prm.grad.numpy(), **tol, err_msg=k)
+
+
+def test_rssm_backward_finite_differences():
+    """Central differences of the (separately pinned) oracle RSSM forward agree
+    with the oracle's RSSM backward, for entries of state0, belief0, the
+    actions and every weight and bias."""
+    w, actions, eps, s0, b0, gr = _rssm_case(43, T=4, B=2)
+    g = oracle.rssm_backward(w, actions, eps, state0=s0, belief0=b0, **gr)
+
+    def loss(w_, a_, s_, b_):
+        m, sd, st, bl = oracle.rssm_unroll(w_, a_, eps, state0=s_, belief0=b_)
+        return float((m * gr["dmeans"]).sum() + (sd * gr["dstds"]).sum()
+                     + (st * gr["dstates"]).sum() + (bl * gr["dbeliefs"]).sum())
+
+    # fp64 loss and exact fp32 offsets: the step only trades the O(h^2)
+    # truncation term against fp64 round-off
+    h = np.float32(2.0 ** -14)
+    rng = np.random.default_rng(9)
+
+    def check(arr, grad, rebuild):
+        for _ in range(3):
+            idx = tuple(int(rng.integers(0, n)) for n in arr.shape)
+            hi, lo = arr.copy(), arr.copy()
+            hi[idx] += h
+            lo[idx] -= h
+            fd = (loss(*rebuild(hi)) - loss(*rebuild(lo))) / (2 * float(h))
+            assert abs(fd - grad[idx]) <= 1e-5 * max(1.0, abs(grad[idx])), (idx, fd, grad[idx])
+
+    check(s0, g["dstate0"], lambda a: (w, actions, a, b0))
+    check(b0, g["dbelief0"], lambda a: (w, actions, s0, a))
+    check(actions, g["dactions"], lambda a: (w, a, s0, b0))
+    for k in oracle.RSSM_WEIGHTS:
+        def rebuild(a, k=k):
+            w2 = dict(w)
+            w2[k] = a
+            return w2, actions, s0, b0
+        check(w[k], g["d" + k], rebuild)
+
+
+def test_rssm_backward_head_only_closed_form():
+    """With only dmeans given and T = 1, the gradient reaching b3 is dmeans
+    summed over rows, and the std half of db3 is zero (a closed form)."""
+    w, actions, eps, s0, b0, gr = _rssm_case(47, T=1, B=3)
+    S = eps.shape[2]
+    g = oracle.rssm_backward(w, actions, eps, state0=s0, belief0=b0, dmeans=gr["dmeans"])
+    np.testing.assert_allclose(g["db3"][:S], gr["dmeans"][0].astype(np.float64).sum(0),
+                               rtol=1e-12, atol=1e-12)
+    assert np.all(g["db3"][S:] == 0.0)
