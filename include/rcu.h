@@ -411,6 +411,34 @@ RCU_API int rssm_unroll(rcu_rssm_t h, int T, int B, const float *state0, const f
                 const float *actions, const float *eps, float *means, float *stds, float *states,
                 float *beliefs, void *stream);
 
+/*
+ * Backward pass through time of rssm_unroll, the training use of the unroll
+ * ("[Feature Request] CUDNN version of RSSM", pytorch/rl issue 366,
+ * Motivation).  Takes rssm_unroll's inputs (state0, belief0, actions, eps; as
+ * there) and the gradient of a loss with respect to its outputs: dmeans,
+ * dstds, dstates [T, B, S] and dbeliefs [T, B, RH], each device or NULL (=
+ * 0).  Writes the gradients dstate0 [B, S], dbelief0 [B, RH] and dactions
+ * [T, B, A] (each may be NULL) and keeps the weight gradients, summed over
+ * rows and steps, for rssm_get_weight_grads.  eps is the noise, an input
+ * that is not differentiated.  fp32 throughout; all device pointers;
+ * asynchronous on `stream`.  The unroll is recomputed inside the call (a
+ * wait that ran out there is reported by rssm_get_status); T, B >= 1.
+ */
+RCU_API int rssm_backward(rcu_rssm_t h, int T, int B, const float *state0, const float *belief0,
+                          const float *actions, const float *eps, const float *dmeans,
+                          const float *dstds, const float *dstates, const float *dbeliefs,
+                          float *dstate0, float *dbelief0, float *dactions, void *stream);
+
+/*
+ * Weight gradients of the last rssm_backward in rssm_set_weights' layouts:
+ * dW1 [Hd, S+A], db1 [Hd], dW_ih [3RH, Hd], dW_hh [3RH, RH], db_ih, db_hh
+ * [3RH], dW2 [Hd, RH], db2 [Hd], dW3 [2S, Hd], db3 [2S]; device, any may be
+ * NULL.  RCU_ERR_STATE before any rssm_backward.
+ */
+RCU_API int rssm_get_weight_grads(rcu_rssm_t h, float *dW1, float *db1, float *dW_ih,
+                                  float *dW_hh, float *db_ih, float *db_hh, float *dW2,
+                                  float *db2, float *dW3, float *db3, void *stream);
+
 RCU_API int rssm_get_status(rcu_rssm_t h, void *stream);
 
 /* Attributes of an RSSM handle: RCU_ATTR_TRACE (1 = record per-step stamps),

@@ -39,7 +39,8 @@ EXPORTED = (
     "rssm_create", "rssm_set_weights", "rssm_unroll", "rssm_get_status",
     "rssm_last_launch_count", "rssm_destroy", "rssm_set_attr", "rssm_get_trace",
     "rssm_set_actor", "rssm_unroll_actor", "rnn_forward_host", "rssm_unroll_host",
-    "rssm_unroll_actor_host", "rnn_backward", "rnn_get_weight_grads",
+    "rssm_unroll_actor_host", "rnn_backward", "rnn_get_weight_grads", "rssm_backward",
+    "rssm_get_weight_grads",
 )
 
 _lib = None
@@ -100,6 +101,8 @@ def load(path: Optional[str] = None):
             "rnn_get_weight_grads": (I, [P, I, I, P, P, P, P, P, P]),
             "rssm_unroll_host": (I, [P, I, I] + [P] * 8 + [P]),
             "rssm_unroll_actor_host": (I, [P, I, I] + [P] * 8 + [P]),
+            "rssm_backward": (I, [P, I, I] + [P] * 12),
+            "rssm_get_weight_grads": (I, [P] + [P] * 11),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -295,6 +298,25 @@ def rssm_unroll(h, T: int, B: int, state0, belief0, actions, eps, means, stds, s
                               _stream(stream)))
 
 
+def rssm_backward(h, T: int, B: int, state0, belief0, actions, eps, dmeans, dstds, dstates,
+                  dbeliefs, dstate0, dbelief0, dactions, stream=None):
+    """Backward pass through time of rssm_unroll (see rcu.h); device tensors."""
+    ins = [_dev(t) for t in (state0, belief0, actions, eps, dmeans, dstds, dstates, dbeliefs)]
+    outs = [_dev(t) for t in (dstate0, dbelief0, dactions)]
+    _check(load().rssm_backward(h, T, B, *[k[1] for k in ins], *[k[1] for k in outs],
+                                _stream(stream)))
+
+
+RSSM_WEIGHT_NAMES = ("W1", "b1", "W_ih", "W_hh", "b_ih", "b_hh", "W2", "b2", "W3", "b3")
+
+
+def rssm_get_weight_grads(h, grads: dict, stream=None):
+    """Copy the last rssm_backward's weight gradients into the device tensors
+    of grads (keys of RSSM_WEIGHT_NAMES; missing or None are skipped)."""
+    outs = [_dev(grads.get(k)) for k in RSSM_WEIGHT_NAMES]
+    _check(load().rssm_get_weight_grads(h, *[k[1] for k in outs], _stream(stream)))
+
+
 def rssm_set_actor(h, actor_hidden: int, Wa1, ba1, Wa2, ba2, stream=None):
     keep = [_dev(t) for t in (Wa1, ba1, Wa2, ba2)]
     _check(load().rssm_set_actor(h, actor_hidden, *[k[1] for k in keep], _stream(stream)))
@@ -473,6 +495,26 @@ class RSSM:
         rssm_unroll(self.h, T, B, state0, belief0, actions, eps, means, stds, states, beliefs,
                     stream)
         return means, stds, states, beliefs
+
+    def backward(self, actions, eps, state0=None, belief0=None, dmeans=None, dstds=None,
+                 dstates=None, dbeliefs=None, stream=None):
+        """Gradients of a loss with the given gradients with respect to the
+        unroll's outputs (None = 0): returns (dstate0, dbelief0, dactions,
+        dict of weight gradients keyed like set_weights)."""
+        T, B, _ = eps.shape
+        dev = eps.device
+        dstate0 = torch.empty((B, self.S), device=dev)
+        dbelief0 = torch.empty((B, self.RH), device=dev)
+        dactions = torch.empty((T, B, self.A), device=dev) if self.A > 0 else None
+        rssm_backward(self.h, T, B, state0, belief0, actions, eps, dmeans, dstds, dstates,
+                      dbeliefs, dstate0, dbelief0, dactions, stream)
+        S, A, Hd, RH = self.S, self.A, self.Hd, self.RH
+        shapes = {"W1": (Hd, S + A), "b1": (Hd,), "W_ih": (3 * RH, Hd), "W_hh": (3 * RH, RH),
+                  "b_ih": (3 * RH,), "b_hh": (3 * RH,), "W2": (Hd, RH), "b2": (Hd,),
+                  "W3": (2 * S, Hd), "b3": (2 * S,)}
+        grads = {k: torch.empty(shapes[k], device=dev) for k in RSSM_WEIGHT_NAMES}
+        rssm_get_weight_grads(self.h, grads, stream)
+        return dstate0, dbelief0, dactions, grads
 
     def set_actor(self, a, device="cuda", stream=None):
         """Actor of the second unroll variant: dict Wa1 [Ha, S+RH], ba1 [Ha],

@@ -1401,6 +1401,9 @@ struct rcu_rssm_s {
   int trace_T = 0;
   // rssm_unroll_host / rssm_unroll_actor_host staging buffers
   DevBuf io_s0, io_b0, io_act, io_eps, io_out[5];
+  // rssm_backward: workspace and the weight gradients of the last call
+  DevBuf bw, gw;
+  bool grads_ready = false;
 };
 
 extern "C" int rssm_set_attr(rcu_rssm_t h, int attr, int64_t value) {
@@ -1599,6 +1602,180 @@ extern "C" int rssm_unroll_actor_host(rcu_rssm_t h, int T, int B, const float *s
                                       float *actions_out, void *stream) {
   return rssm_run_host(h, true, T, B, state0, belief0, nullptr, eps, means, stds, states, beliefs,
                        actions_out, stream);
+}
+
+// Backward pass through time of the unroll with given actions.  The forward
+// is run again (states and beliefs kept); every quantity off the reverse-time
+// chain is then recomputed over all T*B rows (GEMMs, ELU, the GRU gates by
+// the same activation scan as the stacked-RNN backward); the chain runs one
+// step at a time as five batched mat-vecs between elementwise kernels; the
+// weight and action gradients are GEMMs over all rows afterwards.
+extern "C" int rssm_backward(rcu_rssm_t h, int T, int B, const float *state0,
+                             const float *belief0, const float *actions, const float *eps,
+                             const float *dmeans, const float *dstds, const float *dstates,
+                             const float *dbeliefs, float *dstate0, float *dbelief0,
+                             float *dactions, void *stream) {
+  if (!h) return fail(RCU_ERR_INVALID, "rssm_backward: NULL handle");
+  h->launches = 0;
+  if (!h->set) return fail(RCU_ERR_STATE, "rssm_backward: weights not set");
+  if (T < 1 || B < 1 || !eps || (h->A > 0 && !actions))
+    return fail(RCU_ERR_INVALID, "rssm_backward: need T, B >= 1, eps and actions (action_dim > 0)");
+  if ((size_t)T * B > (size_t)INT32_MAX / 8)
+    return fail(RCU_ERR_UNSUPPORTED, "rssm_backward: T*B too large");
+  cudaStream_t s = (cudaStream_t)stream;
+  const int S = h->S, A = h->A, Hd = h->Hd, RH = h->RH, G = 3 * RH, SA = S + A, S2 = 2 * S;
+  const int M = T * B;
+  const int wmax = std::max(std::max(G, Hd), std::max(SA, S2));
+  size_t off = 0;
+  auto take = [&](size_t n) { size_t r = off; off += (n + 63) & ~size_t(63); return r; };
+  const size_t o_mean = take((size_t)M * S), o_std = take((size_t)M * S),
+               o_st = take((size_t)M * S), o_bel = take((size_t)M * RH),
+               o_in = take((size_t)M * SA), o_u = take((size_t)M * Hd), o_x = take((size_t)M * Hd),
+               o_hp = take((size_t)M * RH), o_zi = take((size_t)M * G), o_zh = take((size_t)M * G),
+               o_v = take((size_t)M * Hd), o_q = take((size_t)M * Hd), o_p = take((size_t)M * S2),
+               o_dp = take((size_t)M * S2), o_dv = take((size_t)M * Hd),
+               o_da = take((size_t)M * G), o_dr = take((size_t)M * G), o_du = take((size_t)M * Hd),
+               o_tq = take((size_t)B * Hd), o_thq = take((size_t)B * RH),
+               o_gh = take((size_t)B * RH), o_dhz = take((size_t)B * RH),
+               o_tx = take((size_t)B * Hd), o_cs = take((size_t)B * S),
+               o_w3t = take((size_t)Hd * S2), o_w2t = take((size_t)RH * Hd),
+               o_whht = take((size_t)RH * G), o_wiht = take((size_t)Hd * G),
+               o_w1st = take((size_t)S * Hd), o_w1at = take((size_t)std::max(A, 1) * Hd),
+               o_ta = take((size_t)M * wmax), o_tb = take((size_t)M * wmax),
+               o_csum = take(colsum_scratch_floats(M, wmax));
+  CU(h->bw.ensure(off * 4));
+  float *ws = (float *)h->bw.p;
+  float *means = ws + o_mean, *stds = ws + o_std, *states = ws + o_st, *bel = ws + o_bel;
+  float *IN = ws + o_in, *U = ws + o_u, *X = ws + o_x, *HP = ws + o_hp, *ZI = ws + o_zi,
+        *ZH = ws + o_zh, *V = ws + o_v, *Q = ws + o_q, *Pm = ws + o_p, *DP = ws + o_dp,
+        *DV = ws + o_dv, *DA = ws + o_da, *DR = ws + o_dr, *DU = ws + o_du;
+  float *TQ = ws + o_tq, *THQ = ws + o_thq, *GH = ws + o_gh, *DHZ = ws + o_dhz, *TX = ws + o_tx,
+        *CS = ws + o_cs;
+  float *W3T = ws + o_w3t, *W2T = ws + o_w2t, *WhhT = ws + o_whht, *WihT = ws + o_wiht,
+        *W1sT = ws + o_w1st, *W1aT = ws + o_w1at, *TA = ws + o_ta, *TB = ws + o_tb,
+        *csum = ws + o_csum;
+  const float *W1 = (const float *)h->W1.p, *b1 = (const float *)h->b1.p;
+  const float *Wih = (const float *)h->Wih.p, *Whh = (const float *)h->Whh.p;
+  const float *bih = (const float *)h->bih.p, *bhh = (const float *)h->bhh.p;
+  const float *W2 = (const float *)h->W2.p, *b2 = (const float *)h->b2.p;
+  const float *W3 = (const float *)h->W3.p, *b3 = (const float *)h->b3.p;
+  h->grads_ready = false;
+  // ---- forward again (clears and may set the handle's error word)
+  int rc = rssm_run(h, false, T, B, state0, belief0, actions, eps, means, stds, states, bel,
+                    nullptr, stream);
+  if (rc != RCU_OK) return rc;
+  int launches = h->launches;
+  int *err = (int *)h->ctl.p;
+  cudaError_t e = cudaSuccess;
+  auto gemm = [&](const float *Xp, int ldx, const float *Wp, int ldw, const float *bias, float *Gp,
+                  int ldg, int m, int n, int k) {
+    if (e == cudaSuccess)
+      e = launch_gemm_simt<float, float>(Xp, ldx, Wp, ldw, bias, Gp, ldg, m, nullptr, n, k, s, err);
+    ++launches;
+  };
+  auto tr = [&](const float *in, int R, int C, int ldi, float *out, int ldo) {
+    if (e == cudaSuccess) e = launch_transpose(in, R, C, ldi, out, ldo, s);
+    ++launches;
+  };
+  // ---- everything off the reverse-time chain, over all T*B rows
+  if (e == cudaSuccess) e = launch_rssm_inputs(T, B, S, A, state0, states, actions, IN, s);
+  ++launches;
+  gemm(IN, SA, W1, SA, b1, U, Hd, M, Hd, SA);                    // u = W1 [s, a] + b1
+  if (e == cudaSuccess) e = launch_elu(U, X, (size_t)M * Hd, s);  // x = ELU(u)
+  ++launches;
+  if (belief0) CU(cudaMemcpyAsync(HP, belief0, (size_t)B * RH * 4, cudaMemcpyDeviceToDevice, s));
+  else CU(cudaMemsetAsync(HP, 0, (size_t)B * RH * 4, s));
+  if (T > 1)
+    CU(cudaMemcpyAsync(HP + (size_t)B * RH, bel, (size_t)(T - 1) * B * RH * 4,
+                       cudaMemcpyDeviceToDevice, s));
+  gemm(X, Hd, Wih, Hd, bih, ZI, G, M, G, Hd);                    // input-side gate pre-activations
+  gemm(HP, RH, Whh, RH, bhh, ZH, G, M, G, RH);                   // hidden-side
+  if (e == cudaSuccess) e = launch_bwd_prep(T, B, RH, RCU_GRU, ZI, ZH, nullptr, nullptr, nullptr, s);
+  ++launches;                                                    // ZI <- r, z, n
+  gemm(bel, RH, W2, RH, b2, V, Hd, M, Hd, RH);                   // v = W2 h + b2
+  if (e == cudaSuccess) e = launch_elu(V, Q, (size_t)M * Hd, s);  // q = ELU(v)
+  ++launches;
+  gemm(Q, Hd, W3, Hd, b3, Pm, S2, M, S2, Hd);                    // p = W3 q + b3
+  // transposed weights for the chain's mat-vecs (X W^T form of the GEMM)
+  tr(W3, S2, Hd, Hd, W3T, S2);
+  tr(W2, Hd, RH, RH, W2T, Hd);
+  tr(Whh, G, RH, RH, WhhT, G);
+  tr(Wih, G, Hd, Hd, WihT, G);
+  tr(W1, Hd, S, SA, W1sT, Hd);
+  if (A > 0) tr(W1 + S, Hd, A, SA, W1aT, Hd);
+  if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rssm_backward: recompute: %s", cudaGetErrorString(e));
+  // ---- the reverse-time chain
+  CU(cudaMemsetAsync(GH, 0, (size_t)B * RH * 4, s));
+  CU(cudaMemsetAsync(DHZ, 0, (size_t)B * RH * 4, s));
+  CU(cudaMemsetAsync(CS, 0, (size_t)B * S * 4, s));
+  for (int t = T - 1; t >= 0 && e == cudaSuccess; --t) {
+    const size_t r0 = (size_t)t * B;
+    e = launch_rssm_sample_grad(t, B, S, dmeans, dstds, dstates, eps, Pm, CS, DP, s);
+    ++launches;
+    gemm(DP + r0 * S2, S2, W3T, S2, nullptr, TQ, Hd, B, Hd, S2);      // dq = W3^T dp
+    if (e == cudaSuccess) e = launch_elu_grad(TQ, V + r0 * Hd, DV + r0 * Hd, (size_t)B * Hd, s);
+    ++launches;
+    gemm(DV + r0 * Hd, Hd, W2T, Hd, nullptr, THQ, RH, B, RH, Hd);     // W2^T dv
+    if (e == cudaSuccess)
+      e = launch_rssm_gru_grad(t, B, RH, dbeliefs, THQ, GH, DHZ, ZI, ZH, HP, DA, DR, s);
+    ++launches;
+    gemm(DR + r0 * G, G, WhhT, G, nullptr, GH, RH, B, RH, G);          // W_hh^T dR_t
+    gemm(DA + r0 * G, G, WihT, G, nullptr, TX, Hd, B, Hd, G);          // dx = W_ih^T dA_t
+    if (e == cudaSuccess) e = launch_elu_grad(TX, U + r0 * Hd, DU + r0 * Hd, (size_t)B * Hd, s);
+    ++launches;
+    gemm(DU + r0 * Hd, Hd, W1sT, Hd, nullptr, CS, S, B, S, Hd);       // ds_{t-1} part
+  }
+  if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rssm_backward: recurrence: %s", cudaGetErrorString(e));
+  if (dstate0) CU(cudaMemcpyAsync(dstate0, CS, (size_t)B * S * 4, cudaMemcpyDeviceToDevice, s));
+  if (dbelief0) {
+    CU(cudaMemcpyAsync(dbelief0, GH, (size_t)B * RH * 4, cudaMemcpyDeviceToDevice, s));
+    e = launch_add(dbelief0, DHZ, (size_t)B * RH, s);
+    ++launches;
+  }
+  if (A > 0 && dactions) gemm(DU, Hd, W1aT, Hd, nullptr, dactions, A, M, A, Hd);
+  // ---- weight gradients: dW = dZ^T Y through K-contiguous transposes, db = column sums
+  const size_t nW[10] = {(size_t)Hd * SA, (size_t)Hd, (size_t)G * Hd, (size_t)G * RH, (size_t)G,
+                         (size_t)G, (size_t)Hd * RH, (size_t)Hd, (size_t)S2 * Hd, (size_t)S2};
+  size_t tot = 0;
+  for (size_t v : nW) tot += v;
+  CU(h->gw.ensure(tot * 4));
+  float *gp[10];
+  gp[0] = (float *)h->gw.p;
+  for (int i = 1; i < 10; ++i) gp[i] = gp[i - 1] + nW[i - 1];
+  struct WG { const float *dz; int nz; const float *y; int ny; float *dW; float *db; };
+  const WG wg[5] = {{DU, Hd, IN, SA, gp[0], gp[1]}, {DA, G, X, Hd, gp[2], gp[4]},
+                    {DR, G, HP, RH, gp[3], gp[5]}, {DV, Hd, bel, RH, gp[6], gp[7]},
+                    {DP, S2, Q, Hd, gp[8], gp[9]}};
+  for (const WG &w : wg) {
+    tr(w.dz, M, w.nz, w.nz, TA, M);
+    tr(w.y, M, w.ny, w.ny, TB, M);
+    gemm(TA, M, TB, M, nullptr, w.dW, w.ny, w.nz, w.ny, M);
+    if (e == cudaSuccess) e = launch_colsum(w.dz, M, w.nz, csum, w.db, s);
+    launches += 2;
+  }
+  if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rssm_backward: gradients: %s", cudaGetErrorString(e));
+  h->grads_ready = true;
+  h->launches = launches;
+  return RCU_OK;
+}
+
+extern "C" int rssm_get_weight_grads(rcu_rssm_t h, float *dW1, float *db1, float *dW_ih,
+                                     float *dW_hh, float *db_ih, float *db_hh, float *dW2,
+                                     float *db2, float *dW3, float *db3, void *stream) {
+  if (!h) return fail(RCU_ERR_INVALID, "rssm_get_weight_grads: NULL handle");
+  if (!h->grads_ready) return fail(RCU_ERR_STATE, "rssm_get_weight_grads: no rssm_backward has run");
+  const int S = h->S, A = h->A, Hd = h->Hd, RH = h->RH, G = 3 * RH;
+  const size_t nW[10] = {(size_t)Hd * (S + A), (size_t)Hd, (size_t)G * Hd, (size_t)G * RH,
+                         (size_t)G, (size_t)G, (size_t)Hd * RH, (size_t)Hd, (size_t)2 * S * Hd,
+                         (size_t)2 * S};
+  float *dst[10] = {dW1, db1, dW_ih, dW_hh, db_ih, db_hh, dW2, db2, dW3, db3};
+  const float *src = (const float *)h->gw.p;
+  for (int i = 0; i < 10; ++i) {
+    if (dst[i])
+      CU(cudaMemcpyAsync(dst[i], src, nW[i] * 4, cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
+    src += nW[i];
+  }
+  return RCU_OK;
 }
 
 extern "C" int rssm_get_status(rcu_rssm_t h, void *stream) {

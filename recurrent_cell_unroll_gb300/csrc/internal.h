@@ -145,6 +145,26 @@ cudaError_t launch_gather_steps(const float *in, int ldi, int col0, int w, int T
 // t = len_b - 1, and 0 for t >= len_b; [T][B][w] contiguous, out may be in
 cudaError_t launch_mask_steps(const float *in, int w, int T, int B, const int32_t *lengths,
                               const float *dhn, float *out, cudaStream_t s);
+// ---- rssm_backward.cu: RSSM backward pieces ---------------------------------
+// in [T*B][S+A] = [s_{t-1}, a_t] (s_{-1} = state0, NULL: 0)
+cudaError_t launch_rssm_inputs(int T, int B, int S, int A, const float *state0,
+                               const float *states, const float *actions, float *in,
+                               cudaStream_t s);
+// post = ELU(pre); out = g * ELU'(pre)  (n elements)
+cudaError_t launch_elu(const float *pre, float *post, size_t n, cudaStream_t s);
+cudaError_t launch_elu_grad(const float *g, const float *pre, float *out, size_t n,
+                            cudaStream_t s);
+// step t: dp (rows t*B..) of the sample and head from dmeans/dstds/dstates
+// (NULL = 0), eps, the head output p [T*B][2S] and cs [B][S] (ds from t+1)
+cudaError_t launch_rssm_sample_grad(int t, int B, int S, const float *dmeans, const float *dstds,
+                                    const float *dstates, const float *eps, const float *p,
+                                    const float *cs, float *dp, cudaStream_t s);
+// step t: GRU gate gradients (DA, DR rows t*B..) from dh = dbeliefs_t + dhq +
+// gh + dhz ([B][RH] each); dhz <- z_t * dh
+cudaError_t launch_rssm_gru_grad(int t, int B, int RH, const float *dbeliefs, const float *dhq,
+                                 const float *gh, float *dhz, const float *gates, const float *zh,
+                                 const float *hp, float *DA, float *DR, cudaStream_t s);
+
 struct BwdRecArgs {
   int T, B, H, cell;
   const float *Whh;  // [nG*H][ldw]

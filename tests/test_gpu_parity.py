@@ -918,3 +918,52 @@ def test_backward_errors():
         binding.rnn_backward(net.h, spec.T, spec.B, x, None, None, None, dy, None, None, None, None,
                              None)
     net.close()
+
+
+# ----------------------------------------------------------------------------- RSSM backward
+
+RSSM_BWD_SPECS = [
+    wl.RSSM_B50,
+    wl.RSSM_B50.scaled(T=7, B=3, state_dim=5, action_dim=0, hidden=33, rnn_hidden=17,
+                       state0_std=1.0, belief0_std=0.5),
+    wl.RSSM_B50.scaled(T=6, B=70, state_dim=13, action_dim=5, hidden=72, rnn_hidden=40,
+                       state0_std=1.0, belief0_std=0.5),
+]
+
+
+@pytest.mark.parametrize("spec", RSSM_BWD_SPECS,
+                         ids=lambda s: f"T{s.T}-B{s.B}-S{s.state_dim}-A{s.action_dim}-H{s.hidden}")
+@pytest.mark.parametrize("which", ["all", "beliefs_only"])
+def test_rssm_backward_parity(spec, which):
+    """rssm_backward + rssm_get_weight_grads against the oracle's RSSM backward
+    (per tensor: max|gpu - ref| / max|ref| <= 1e-4); gradients given for every
+    output, or for the beliefs alone (the others NULL)."""
+    inp = wl.make_rssm_inputs(spec, seed=22)
+    g = torch.Generator().manual_seed(97)
+    T, B, S, RH = spec.T, spec.B, spec.state_dim, spec.rnn_hidden
+    grads = {k: torch.randn((T, B, n), generator=g)
+             for k, n in (("dmeans", S), ("dstds", S), ("dstates", S), ("dbeliefs", RH))}
+    if which == "beliefs_only":
+        grads = {"dbeliefs": grads["dbeliefs"]}
+    dev = torch.device("cuda")
+    m = binding.RSSM(spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden)
+    m.set_weights(inp["weights"])
+    with pytest.raises(RuntimeError, match="no rssm_backward"):
+        binding.rssm_get_weight_grads(m.h, {})
+    d = lambda t: None if t is None else t.to(dev)
+    dstate0, dbelief0, dactions, wg = m.backward(
+        d(inp["actions"]), d(inp["eps"]), d(inp["state0"]), d(inp["belief0"]),
+        **{k: d(v) for k, v in grads.items()})
+    torch.cuda.synchronize()
+    assert binding.rssm_get_status(m.h) == 0
+    ref = oracle.rssm_backward(inp["weights"], inp["actions"], inp["eps"], state0=inp["state0"],
+                               belief0=inp["belief0"], **grads)
+    pairs = [("dstate0", dstate0), ("dbelief0", dbelief0)]
+    if spec.action_dim > 0:
+        pairs.append(("dactions", dactions))
+    pairs += [("d" + k, wg[k]) for k in binding.RSSM_WEIGHT_NAMES]
+    for name, got in pairs:
+        e = _rel(got.cpu().numpy().astype(np.float64), ref[name])
+        print(f"{name}: rel {e:.2e}")
+        assert e <= BWD_REL, f"{name}: relative max error {e:.3e}"
+    m.close()
