@@ -36,7 +36,7 @@ from recurrent_cell_unroll_gb300 import workloads as wl  # noqa: E402
 WORKLOADS = {
     "lstm": wl.LSTM_T80, "rssm": wl.RSSM_B50, "lstmp": wl.LSTMP_2L,
     "bilstm": wl.BILSTM_VAR, "gru": wl.GRU_3L, "rssm_actor": wl.RSSM_ACTOR,
-    "lstm_train": wl.LSTM_TRAIN,
+    "lstm_train": wl.LSTM_TRAIN, "bilstm_train": wl.BILSTM_TRAIN,
 }
 METRIC = "(batch×timesteps)/s"
 UNIT = "(B·T)/s"
@@ -112,13 +112,16 @@ def kernel_flops(spec, inp) -> dict:
         rec.append(2 * M * D * (nG * H * Ho + (P * H if P else 0)))
     out = {"input_gemm": gemm, "recurrent": rec}
     if getattr(spec, "train", False):
-        # backward through time: dh recurrence W_hh^T dz, dW_ih, dW_hh, dX; the
-        # recompute GEMMs repeat the forward's (counted, they run)
+        # backward through time, per (layer, direction): the dh recurrence
+        # (W_hh^T dz, or (W_hh W_hr)^T dz with a projection: width H either
+        # way), dW_ih, dW_hh, dX; the recompute GEMMs repeat the forward's
+        # (counted, they run).  M counts processed row-steps only.
         G = nG * H
-        ks = [spec.in_dim if layer == 0 else H for layer in range(spec.layers)]
-        out["bwd_recompute_gemm"] = [2 * M * G * (k + H) for k in ks]
+        ks = [spec.in_dim if layer == 0 else D * Ho for layer in range(spec.layers)
+              for _ in range(D)]
+        out["bwd_recompute_gemm"] = [2 * M * G * (k + Ho) for k in ks]
         out["bwd_recurrent"] = [2 * M * G * H for _ in ks]
-        out["bwd_weight_gemm"] = [2 * M * G * (k + H) for k in ks]
+        out["bwd_weight_gemm"] = [2 * M * G * (k + Ho) for k in ks]
         out["bwd_dx_gemm"] = [2 * M * G * k for k in ks]
     return out
 
@@ -307,24 +310,28 @@ def make_runner(spec, inp, dev, tc_ksplit=0):
 
 def make_train_runner(spec, inp, dev, net, d):
     """A training pass: rnn_backward (which runs the forward again keeping every
-    layer's output) and the weight gradients of every layer."""
+    layer's output) and the weight gradients of every layer and direction."""
     from recurrent_cell_unroll_gb300 import binding
-    T, B, H, L = spec.T, spec.B, spec.hidden, spec.layers
-    nG = spec.nG
+    T, B, H, L, D, Ho, P = spec.T, spec.B, spec.hidden, spec.layers, spec.D, spec.Hout, spec.proj
+    G = spec.nG * H
     dy = inp["dy"].to(dev)
     dx = torch.empty_like(d["x"])
-    dh0 = torch.empty((L, B, H), device=dev)
-    dc0 = torch.empty_like(dh0) if spec.cell == "lstm" else None
-    grads = []
-    for layer in range(L):
-        k = spec.in_dim if layer == 0 else H
-        grads.append([torch.empty((nG * H, k), device=dev), torch.empty((nG * H, H), device=dev),
-                      torch.empty((nG * H,), device=dev), torch.empty((nG * H,), device=dev)])
+    dh0 = torch.empty((L * D, B, Ho), device=dev)
+    dc0 = torch.empty((L * D, B, H), device=dev) if spec.cell == "lstm" else None
+    grads = []  # over layer * D + direction: dW_ih, dW_hh, db_ih, db_hh, dW_hr
+    for i in range(L * D):
+        k = spec.in_dim if i // D == 0 else D * Ho
+        grads.append([torch.empty((G, k), device=dev), torch.empty((G, Ho), device=dev),
+                      torch.empty((G,), device=dev), torch.empty((G,), device=dev),
+                      torch.empty((P, H), device=dev) if P else None])
 
     def step():
-        binding.rnn_backward(net.h, T, B, d["x"], None, d["h0"], d["c0"], dy, None, None, dx, dh0, dc0)
-        for layer in range(L):
-            binding.rnn_get_weight_grads(net.h, layer, *grads[layer])
+        binding.rnn_backward(net.h, T, B, d["x"], d["lengths"], d["h0"], d["c0"], dy, None, None,
+                             dx, dh0, dc0)
+        for i in range(L * D):
+            layer, direction = divmod(i, D)
+            binding.rnn_get_weight_grads(net.h, layer, *grads[i][:4], dW_hr=grads[i][4],
+                                         direction=direction)
 
     def launches():
         return net.launch_count()
@@ -342,12 +349,16 @@ def make_train_runner(spec, inp, dev, net, d):
         # no host-buffer form of the backward: pinned host tensors copied in and
         # out around the device call, all on the launching stream
         hin = {"x": inp["x"].contiguous().pin_memory(), "dy": inp["dy"].contiguous().pin_memory()}
-        outs = [dx] + [g for gl in grads for g in gl]
+        if d["lengths"] is not None:
+            hin["lengths"] = inp["lengths"].contiguous().pin_memory()
+        outs = [dx] + [g for gl in grads for g in gl if g is not None]
         hout = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
 
         def call():
             d["x"].copy_(hin["x"], non_blocking=True)
             dy.copy_(hin["dy"], non_blocking=True)
+            if "lengths" in hin:
+                d["lengths"].copy_(hin["lengths"], non_blocking=True)
             step()
             for o, hbuf in zip(outs, hout):
                 hbuf.copy_(o, non_blocking=True)
@@ -610,7 +621,9 @@ def oracle_sample(spec, inp, rows, threads):
         sub = (lambda t, dim: None if t is None else t[:, sel] if dim == 1 else t[sel])
         oracle.rnn_backward(oracle.LSTM if spec.cell == "lstm" else oracle.GRU,
                             sub(inp["x"], 1), inp["weights"], sub(inp["dy"], 1),
-                            hidden=spec.hidden, h0=sub(inp["h0"], 1), c0=sub(inp["c0"], 1),
+                            hidden=spec.hidden, proj=spec.proj, bidirectional=spec.bidir,
+                            lengths=sub(inp["lengths"], 0), h0=sub(inp["h0"], 1),
+                            c0=sub(inp["c0"], 1), bf16_weights=spec.dtype == "bf16",
                             threads=threads)
     else:
         oracle.rnn_forward(oracle.LSTM if spec.cell == "lstm" else oracle.GRU, inp["x"],

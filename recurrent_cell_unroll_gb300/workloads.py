@@ -89,9 +89,12 @@ GRU_3L = RnnSpec("gru_bf16_3L_T512_B256_1024", "gru", 3, 1024, 1024, T=512, B=25
 # shape (256 -> 512, B = 64, T = 500); dy ~ N(0, 1)
 LSTM_TRAIN = RnnSpec("lstm_train_f32_T500_B64_256x512", "lstm", 1, 256, 512, T=500, B=64,
                      train=True)
+# forward + backward through time of the variable-length bidirectional shape
+# itself (the same x, lengths and weights as BILSTM_VAR; dy ~ N(0, 1))
+BILSTM_TRAIN = BILSTM_VAR.scaled(name="bilstm_train_f32_varlen_B64_T500_256x512", train=True)
 
 WORKLOADS = {s.name: s for s in (LSTM_T80, RSSM_B50, LSTMP_2L, BILSTM_VAR, GRU_3L,
-                                  RSSM_ACTOR, LSTM_TRAIN)}
+                                  RSSM_ACTOR, LSTM_TRAIN, BILSTM_TRAIN)}
 
 
 def _uniform(g, shape, bound):

@@ -123,6 +123,26 @@ def test_training_flops_are_forward_plus_bptt():
     assert "dy" in inp and inp["dy"].shape == (2, 2, H)
 
 
+def test_bidirectional_varlen_training_flops():
+    """Bidirectional, variable length: one entry per (layer, direction), M =
+    the processed row-steps (the sum of the lengths), the upper layer's K =
+    2 * hidden; the training draws leave the forward workload's inputs
+    unchanged."""
+    spec = wl.BILSTM_TRAIN.scaled(layers=2, T=6, B=3, varlen=(2, 6))
+    inp = wl.make_rnn_inputs(spec, seed=4)
+    fwd = wl.make_rnn_inputs(spec.scaled(train=False), seed=4)
+    assert torch.equal(inp["x"], fwd["x"]) and torch.equal(inp["lengths"], fwd["lengths"])
+    fl = bench.kernel_flops(spec, inp)
+    M, H, K = int(inp["lengths"].sum()), spec.hidden, spec.in_dim
+    G = 4 * H
+    ks = [K, K, 2 * H, 2 * H]
+    assert fl["bwd_recompute_gemm"] == [2 * M * G * (k + H) for k in ks]
+    assert fl["bwd_recurrent"] == [2 * M * G * H] * 4
+    assert fl["bwd_weight_gemm"] == [2 * M * G * (k + H) for k in ks]
+    assert fl["bwd_dx_gemm"] == [2 * M * G * k for k in ks]
+    assert inp["dy"].shape == (6, 3, 2 * H)
+
+
 def test_traffic_table_names_real_workloads_and_kernels():
     """Every captured traffic entry belongs to a bench workload and to a kernel
     name the roofline can report for it."""
