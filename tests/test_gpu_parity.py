@@ -967,3 +967,35 @@ def test_rssm_backward_parity(spec, which):
         print(f"{name}: rel {e:.2e}")
         assert e <= BWD_REL, f"{name}: relative max error {e:.3e}"
     m.close()
+
+
+# ----------------------------------------------------------------------------- full-size training pass
+
+@pytest.mark.parametrize("spec", [wl.LSTM_TRAIN, wl.BILSTM_TRAIN], ids=lambda s: s.name)
+def test_training_pass_full_size(spec):
+    """The training workloads at their full size, through rnn_backward as the
+    benchmark calls it (seed-0 inputs, the workload's dy, no dh_n / dc_n):
+    every gradient tensor against the oracle's backward over all rows."""
+    inp = wl.make_rnn_inputs(spec, seed=0)
+    dev = torch.device("cuda")
+    net = binding.RNN.from_spec(spec)
+    net.set_weights(inp["weights"])
+    d = lambda t: None if t is None else t.to(dev)
+    dx, dh0, dc0, grads = net.backward(d(inp["x"]), d(inp["dy"]), lengths=d(inp["lengths"]),
+                                       h0=d(inp["h0"]), c0=d(inp["c0"]))
+    torch.cuda.synchronize()
+    assert net.status() == 0
+    ref = oracle.rnn_backward(_cell(spec), inp["x"], inp["weights"], inp["dy"],
+                              hidden=spec.hidden, proj=spec.proj, bidirectional=spec.bidir,
+                              lengths=inp["lengths"], h0=inp["h0"], c0=inp["c0"])
+    pairs = [("dx", dx, ref["dx"]), ("dh0", dh0, ref["dh0"])]
+    if spec.cell == "lstm":
+        pairs.append(("dc0", dc0, ref["dc0"]))
+    for i in range(spec.layers * spec.D):
+        for k in ("w_ih", "w_hh", "b_ih", "b_hh"):
+            pairs.append((f"d{k}[{i}]", grads[i][k], ref["d" + k][i]))
+    for name, got, want in pairs:
+        e = _rel(got.cpu().numpy().astype(np.float64), want)
+        print(f"{name}: rel {e:.2e}")
+        assert e <= BWD_REL, f"{name}: relative max error {e:.3e}"
+    net.close()
