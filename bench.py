@@ -36,7 +36,7 @@ from recurrent_cell_unroll_gb300 import workloads as wl  # noqa: E402
 WORKLOADS = {
     "lstm": wl.LSTM_T80, "rssm": wl.RSSM_B50, "lstmp": wl.LSTMP_2L,
     "bilstm": wl.BILSTM_VAR, "gru": wl.GRU_3L, "rssm_actor": wl.RSSM_ACTOR,
-    "lstm_train": wl.LSTM_TRAIN, "bilstm_train": wl.BILSTM_TRAIN,
+    "lstm_train": wl.LSTM_TRAIN, "bilstm_train": wl.BILSTM_TRAIN, "rssm_train": wl.RSSM_TRAIN,
 }
 METRIC = "(batch×timesteps)/s"
 UNIT = "(B·T)/s"
@@ -99,10 +99,19 @@ def kernel_flops(spec, inp) -> dict:
     """Algorithmic FLOPs per launch of each kernel kind (2 per multiply-add)."""
     if isinstance(spec, wl.RssmSpec):
         S, A, Hd, RH = spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden
-        per = 2 * (Hd * (S + A) + 3 * RH * Hd + 3 * RH * RH + Hd * RH + 2 * S * Hd)
+        prior = 2 * (Hd * (S + A) + 3 * RH * Hd + 3 * RH * RH + Hd * RH + 2 * S * Hd)
         Hx = spec.actor_hidden
-        per += 2 * (Hx * (S + RH) + A * Hx)
-        return {"rssm": [per * spec.B * spec.T]}
+        per = prior + 2 * (Hx * (S + RH) + A * Hx)
+        rs = spec.B * spec.T
+        if not spec.train:
+            return {"rssm": [per * rs]}
+        # training pass, per phase of rssm_backward (names of its timed spans):
+        # the unroll again; the same products over all rows; the reverse-time
+        # chain (W3^T, W2^T, W_hh^T, W_ih^T and the state columns of W1^T per
+        # row-step); the weight gradients and the action gradient
+        chain = 2 * (2 * S * Hd + Hd * RH + 3 * RH * RH + 3 * RH * Hd + S * Hd)
+        return {"rssm_unroll": [per * rs], "rssm_bwd_recompute": [prior * rs],
+                "rssm_bwd_chain": [chain * rs], "rssm_bwd_grads": [(prior + 2 * A * Hd) * rs]}
     M = active_rows(spec, inp)
     D, nG, H, Ho, P = spec.D, spec.nG, spec.hidden, spec.Hout, spec.proj
     gemm, rec = [], []
@@ -214,8 +223,67 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- our arm
 
+def make_rssm_train_runner(spec, inp, dev):
+    """A training pass of the RSSM unroll: rssm_backward (which runs the unroll
+    again) and the weight gradients."""
+    from recurrent_cell_unroll_gb300 import binding
+    m = binding.RSSM(spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden)
+    m.set_weights(inp["weights"], device=dev)
+    names = ("actions", "eps", "state0", "belief0", "dmeans", "dstds", "dstates", "dbeliefs")
+    d = {k: (None if inp[k] is None else inp[k].to(dev)) for k in names}
+    T, B, S, A, RH = spec.T, spec.B, spec.state_dim, spec.action_dim, spec.rnn_hidden
+    dstate0 = torch.empty((B, S), device=dev)
+    dbelief0 = torch.empty((B, RH), device=dev)
+    dactions = torch.empty((T, B, A), device=dev) if A > 0 else None
+    Hd = spec.hidden
+    shapes = {"W1": (Hd, S + A), "b1": (Hd,), "W_ih": (3 * RH, Hd), "W_hh": (3 * RH, RH),
+              "b_ih": (3 * RH,), "b_hh": (3 * RH,), "W2": (Hd, RH), "b2": (Hd,),
+              "W3": (2 * S, Hd), "b3": (2 * S,)}
+    grads = {k: torch.empty(shapes[k], device=dev) for k in binding.RSSM_WEIGHT_NAMES}
+
+    def step():
+        binding.rssm_backward(m.h, T, B, d["state0"], d["belief0"], d["actions"], d["eps"],
+                              d["dmeans"], d["dstds"], d["dstates"], d["dbeliefs"], dstate0,
+                              dbelief0, dactions)
+        binding.rssm_get_weight_grads(m.h, grads)
+
+    def launches():
+        return binding.rssm_last_launch_count(m.h)
+
+    def profile_on():
+        m.set_attr(binding.RCU_ATTR_PROFILE, 1)
+        binding.rssm_profile_reset(m.h)
+
+    def profile_read():
+        prof = m.profile()
+        m.set_attr(binding.RCU_ATTR_PROFILE, 0)
+        return prof
+
+    def e2e_io():
+        # no host-buffer form of the backward: pinned host tensors copied in and
+        # out around the device call, all on the launching stream
+        hin = {k: inp[k].contiguous().pin_memory() for k in names if inp[k] is not None}
+        outs = [dstate0, dbelief0] + ([dactions] if dactions is not None else []) + \
+            list(grads.values())
+        hout = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+
+        def call():
+            for k, v in hin.items():
+                d[k].copy_(v, non_blocking=True)
+            step()
+            for o, hbuf in zip(outs, hout):
+                hbuf.copy_(o, non_blocking=True)
+        return list(hin.values()), hout, call
+
+    def status():
+        return binding.rssm_get_status(m.h)
+    return step, launches, profile_on, profile_read, e2e_io, status, m
+
+
 def make_runner(spec, inp, dev, tc_ksplit=0):
     from recurrent_cell_unroll_gb300 import binding
+    if isinstance(spec, wl.RssmSpec) and spec.train:
+        return make_rssm_train_runner(spec, inp, dev)
     if isinstance(spec, wl.RssmSpec):
         m = binding.RSSM(spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden)
         m.set_weights(inp["weights"], device=dev)
@@ -396,7 +464,7 @@ def roofline(spec, inp, prof, peaks, nsm, step_ms=None):
 
 
 def _roofline(spec, inp, prof, peaks, nsm, step_ms=None):
-    if isinstance(spec, wl.RssmSpec):
+    if isinstance(spec, wl.RssmSpec) and not spec.train:
         # one kernel per step: its launch time is the event-timed step
         per_launch = kernel_flops(spec, inp)["rssm"][0]
         achieved = per_launch / (step_ms / 1e3) / 1e12
@@ -417,7 +485,7 @@ def _roofline(spec, inp, prof, peaks, nsm, step_ms=None):
     per_launch = sum(fl[kind]) / len(fl[kind])
     avg_s = ms / 1e3 / n
     achieved = per_launch / avg_s / 1e12
-    if spec.dtype == "bf16":
+    if getattr(spec, "dtype", "f32") == "bf16":
         peak, bound, note = peaks["bf16_tflops_sustained"], "tensor", \
             f"bf16 dense, sustained, {peaks['source']}"
     else:
@@ -508,7 +576,9 @@ def run_ours(args, spec, rank, local, ws):
             raise RuntimeError(f"device status {st} in the end-to-end loop")
         e2e = {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-               "call": ("rssm_unroll_actor_host" if getattr(spec, "actor_hidden", 0) else
+               "call": ("rssm_backward + rssm_get_weight_grads, pinned host copies on the stream"
+                        if getattr(spec, "train", False) else
+                        "rssm_unroll_actor_host" if getattr(spec, "actor_hidden", 0) else
                         "rssm_unroll_host") if isinstance(spec, wl.RssmSpec) else
                ("rnn_backward + rnn_get_weight_grads, pinned host copies on the stream"
                 if getattr(spec, "train", False) else "rnn_forward_host"),
@@ -564,6 +634,10 @@ def compulsory_bytes(spec, inp) -> int:
         w += Hx * (S + RH + 1) + A * (Hx + 1)
         # actions are read when given, written when the actor makes them
         io = spec.T * spec.B * (A + S + 3 * S + RH)
+        if spec.train:
+            # weights in, their gradients out; actions, eps and the four output
+            # gradients in, the action gradient out
+            return 4 * (2 * w + io + spec.T * spec.B * A)
         return 4 * (w + io)
     es = 2 if spec.dtype == "bf16" else 4
     D, nG, H, Ho = spec.D, spec.nG, spec.hidden, spec.Hout
@@ -588,7 +662,8 @@ def workload_config(spec, inp, ws):
          else "L2 flushed between timed steps (256 MB write)"}
     if isinstance(spec, wl.RssmSpec):
         c.update(state_dim=spec.state_dim, action_dim=spec.action_dim, hidden=spec.hidden,
-                 rnn_hidden=spec.rnn_hidden, actor_hidden=spec.actor_hidden or None)
+                 rnn_hidden=spec.rnn_hidden, actor_hidden=spec.actor_hidden or None,
+                 train=spec.train or None)
     else:
         c.update(cell=spec.cell, layers=spec.layers, in_dim=spec.in_dim, hidden=spec.hidden,
                  proj=spec.proj, bidirectional=spec.bidir, train=spec.train or None,
@@ -610,7 +685,14 @@ def input_bytes(spec, inp):
 def oracle_sample(spec, inp, rows, threads):
     import oracle
     t0 = time.perf_counter()
-    if isinstance(spec, wl.RssmSpec) and spec.actor_hidden:
+    if isinstance(spec, wl.RssmSpec) and spec.train:
+        sel = list(rows)
+        sub = (lambda t, dim: None if t is None else t[:, sel] if dim == 1 else t[sel])
+        oracle.rssm_backward(inp["weights"], sub(inp["actions"], 1), sub(inp["eps"], 1),
+                             state0=sub(inp["state0"], 0), belief0=sub(inp["belief0"], 0),
+                             **{k: sub(inp[k], 1) for k in ("dmeans", "dstds", "dstates",
+                                                            "dbeliefs")})
+    elif isinstance(spec, wl.RssmSpec) and spec.actor_hidden:
         oracle.rssm_unroll_actor(inp["weights"], inp["actor"], inp["eps"], state0=inp["state0"],
                                  belief0=inp["belief0"], rows=rows, threads=threads)
     elif isinstance(spec, wl.RssmSpec):
@@ -641,11 +723,20 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def oracle_serial(spec) -> bool:
+    """The RSSM backward oracle takes its rows one after another on one thread
+    (its weight gradients sum over them)."""
+    return isinstance(spec, wl.RssmSpec) and spec.train
+
+
 def sample_rows(spec, inp, cores, budget_s):
-    """Rows for a bounded oracle sample: at most one per core, at least one; when a
-    single row already exceeds the budget, one row."""
+    """Rows for a bounded oracle sample: at most one per core (any number for a
+    one-thread oracle), at least one; when a single row already exceeds the
+    budget, one row."""
     per_row = oracle_sample(spec, inp, [0], 1)
-    n = max(1, min(spec.B, cores, int(budget_s * cores / max(per_row, 1e-9))))
+    par = 1 if oracle_serial(spec) else cores
+    cap = spec.B if oracle_serial(spec) else cores
+    n = max(1, min(spec.B, cap, int(budget_s * par / max(per_row, 1e-9))))
     return list(range(n)), per_row
 
 
@@ -654,7 +745,7 @@ def cpu_baseline(spec, inp, budget_s=20.0):
     oracle.build()
     cores = cpu_cores()
     rows, _ = sample_rows(spec, inp, cores, budget_s)
-    threads = min(cores, len(rows))
+    threads = 1 if oracle_serial(spec) else min(cores, len(rows))
     t = oracle_sample(spec, inp, rows, threads)
     value = len(rows) * spec.T / t
     return {"value": round(value, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -672,7 +763,7 @@ def run_reference(args, spec):
     # size each step so that warm-up + timed steps stay within ~3 minutes
     budget = max(1.0, min(20.0, 180.0 / max(1, args.steps + args.warmup)))
     rows, _ = sample_rows(spec, inp, cores, budget)
-    threads = min(cores, len(rows))
+    threads = 1 if oracle_serial(spec) else min(cores, len(rows))
     for _ in range(args.warmup):
         oracle_sample(spec, inp, rows, threads)
     t = 0.0

@@ -91,8 +91,10 @@ typedef struct rcu_rssm_s *rcu_rssm_t;
                                          2 = CTA pairs, 4 = clusters of 4; a split that
                                          does not fit falls back to the next smaller) */
 #define RCU_ATTR_PROFILE 4            /* 1 = record a CUDA event pair around every kernel
-                                         this handle launches (on the launching stream);
-                                         read the totals with rnn_profile_entry */
+                                         this handle launches (RSSM handle: around each
+                                         named phase of launches), on the launching
+                                         stream; read the totals with rnn_profile_entry /
+                                         rssm_profile_entry */
 #define RCU_ATTR_HOST_CHUNKS 8        /* rnn_forward_host: chunks of steps whose host<->device
                                          copies overlap the other chunks' compute (0 =
                                          automatic, 1 = none, up to RCU_MAX_HOST_CHUNKS;
@@ -442,8 +444,22 @@ RCU_API int rssm_get_weight_grads(rcu_rssm_t h, float *dW1, float *db1, float *d
 RCU_API int rssm_get_status(rcu_rssm_t h, void *stream);
 
 /* Attributes of an RSSM handle: RCU_ATTR_TRACE (1 = record per-step stamps),
- * RCU_ATTR_BARRIER_TIMEOUT_NS (bound on each wait for a broadcast vector). */
+ * RCU_ATTR_BARRIER_TIMEOUT_NS (bound on each wait for a broadcast vector),
+ * RCU_ATTR_PROFILE (1 = time named phases), RCU_ATTR_TEST_DROP_ARRIVAL. */
 RCU_API int rssm_set_attr(rcu_rssm_t h, int attr, int64_t value);
+
+/*
+ * Phase timing collected while RCU_ATTR_PROFILE is on, as rnn_profile_entry:
+ * entry i gives the phase's name, its summed event-measured duration in ms
+ * and how many times it ran.  Phases: "rssm_unroll" / "rssm_unroll_actor"
+ * (the unroll kernel), and in rssm_backward "rssm_bwd_recompute" (everything
+ * off the reverse-time chain), "rssm_bwd_chain" (the whole reverse-time
+ * sweep, all its launches) and "rssm_bwd_grads" (weight and input gradients).
+ * rssm_profile_reset clears the totals.
+ */
+RCU_API int rssm_profile_entry(rcu_rssm_t h, int i, const char **name, double *total_ms,
+                               int64_t *count);
+RCU_API int rssm_profile_reset(rcu_rssm_t h);
 
 /*
  * Step trace of the last traced rssm_unroll or rssm_unroll_actor: for each

@@ -40,7 +40,7 @@ EXPORTED = (
     "rssm_last_launch_count", "rssm_destroy", "rssm_set_attr", "rssm_get_trace",
     "rssm_set_actor", "rssm_unroll_actor", "rnn_forward_host", "rssm_unroll_host",
     "rssm_unroll_actor_host", "rnn_backward", "rnn_get_weight_grads", "rssm_backward",
-    "rssm_get_weight_grads",
+    "rssm_get_weight_grads", "rssm_profile_entry", "rssm_profile_reset",
 )
 
 _lib = None
@@ -103,6 +103,9 @@ def load(path: Optional[str] = None):
             "rssm_unroll_actor_host": (I, [P, I, I] + [P] * 8 + [P]),
             "rssm_backward": (I, [P, I, I] + [P] * 12),
             "rssm_get_weight_grads": (I, [P] + [P] * 11),
+            "rssm_profile_entry": (I, [P, I, ctypes.POINTER(ctypes.c_char_p),
+                                       ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64)]),
+            "rssm_profile_reset": (I, [P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -230,6 +233,19 @@ def rnn_profile_entry(h, i: int):
 
 def rnn_profile_reset(h):
     _check(load().rnn_profile_reset(h))
+
+
+def rssm_profile_entry(h, i: int):
+    """(name, total_ms, count) of RSSM profile entry i, or None past the end."""
+    name, ms, n = ctypes.c_char_p(), ctypes.c_double(), ctypes.c_int64()
+    rc = load().rssm_profile_entry(h, i, ctypes.byref(name), ctypes.byref(ms), ctypes.byref(n))
+    if rc != RCU_OK:
+        return None
+    return name.value.decode(), ms.value, n.value
+
+
+def rssm_profile_reset(h):
+    _check(load().rssm_profile_reset(h))
 
 
 def rnn_get_trace(h, n_steps: int, stream=None):
@@ -540,6 +556,19 @@ class RSSM:
 
     def launch_count(self) -> int:
         return rssm_last_launch_count(self.h)
+
+    def set_attr(self, attr, value):
+        rssm_set_attr(self.h, attr, value)
+
+    def profile(self) -> dict:
+        """{phase name: (total_ms, count)} recorded while RCU_ATTR_PROFILE is on."""
+        out, i = {}, 0
+        while True:
+            e = rssm_profile_entry(self.h, i)
+            if e is None:
+                return out
+            out[e[0]] = (e[1], e[2])
+            i += 1
 
     def close(self):
         if self.h:

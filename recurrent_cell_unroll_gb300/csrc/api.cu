@@ -175,7 +175,70 @@ struct LayerDirW {
   bool set = false;
 };
 
-struct rcu_rnn_s {
+// Opt-in timing of named spans of launches (one kernel, or a group) with CUDA
+// events recorded on the launching stream (RCU_ATTR_PROFILE); totals per name
+// are read with *_profile_entry.
+struct EventProfiler {
+  bool profile = false;
+  struct Pending { const char *name; cudaEvent_t a, b; };
+  std::vector<Pending> pending;
+  std::vector<cudaEvent_t> pool;
+  std::vector<std::pair<std::string, std::pair<double, long>>> totals;
+  const char *open_name = nullptr;
+  cudaEvent_t open_ev = nullptr;
+  cudaEvent_t get_event() {
+    if (!pool.empty()) { cudaEvent_t e = pool.back(); pool.pop_back(); return e; }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+  void prof_begin(const char *name, cudaStream_t s) {
+    if (!profile) return;
+    open_name = name;
+    open_ev = get_event();
+    cudaEventRecord(open_ev, s);
+  }
+  void prof_end(cudaStream_t s) {
+    if (!profile || !open_ev) return;
+    cudaEvent_t b = get_event();
+    cudaEventRecord(b, s);
+    pending.push_back({open_name, open_ev, b});
+    open_ev = nullptr;
+  }
+  void collect() {
+    for (auto &p : pending) {
+      cudaEventSynchronize(p.b);
+      float ms = 0.f;
+      cudaEventElapsedTime(&ms, p.a, p.b);
+      bool found = false;
+      for (auto &t : totals)
+        if (t.first == p.name) { t.second.first += ms; t.second.second += 1; found = true; break; }
+      if (!found) totals.push_back({p.name, {ms, 1L}});
+      pool.push_back(p.a);
+      pool.push_back(p.b);
+    }
+    pending.clear();
+  }
+  int entry(int i, const char **name, double *total_ms, int64_t *count) {
+    collect();
+    if (i < 0 || i >= (int)totals.size()) return fail(RCU_ERR_INVALID, "no profile entry %d", i);
+    if (name) *name = totals[i].first.c_str();
+    if (total_ms) *total_ms = totals[i].second.first;
+    if (count) *count = totals[i].second.second;
+    return RCU_OK;
+  }
+  void reset() {
+    collect();
+    totals.clear();
+  }
+  ~EventProfiler() {
+    for (auto &p : pending) { cudaEventDestroy(p.a); cudaEventDestroy(p.b); }
+    if (open_ev) cudaEventDestroy(open_ev);
+    for (auto e : pool) cudaEventDestroy(e);
+  }
+};
+
+struct rcu_rnn_s : EventProfiler {
   int cell, layers, D, in_dim, H, P, Hout, nG, dtype;
   int device, nsm;
   // SIMT plan
@@ -230,51 +293,12 @@ struct rcu_rnn_s {
   bool trace = false;
   DevBuf trace_buf;
   int trace_T = 0;
-  // opt-in per-kernel timing with CUDA events on the launching stream
-  bool profile = false;
-  struct Pending { const char *name; cudaEvent_t a, b; };
-  std::vector<Pending> pending;
-  std::vector<cudaEvent_t> pool;
-  std::vector<std::pair<std::string, std::pair<double, long>>> totals;
-  const char *open_name = nullptr;
-  cudaEvent_t open_ev = nullptr;
-  cudaEvent_t get_event() {
-    if (!pool.empty()) { cudaEvent_t e = pool.back(); pool.pop_back(); return e; }
-    cudaEvent_t e = nullptr;
-    cudaEventCreate(&e);
-    return e;
-  }
-  void begin(const char *name, cudaStream_t s) {
-    if (!profile) return;
-    open_name = name;
-    open_ev = get_event();
-    cudaEventRecord(open_ev, s);
-  }
+  void begin(const char *name, cudaStream_t s) { prof_begin(name, s); }
   void end(cudaStream_t s) {
     ++launches;
-    if (!profile || !open_ev) return;
-    cudaEvent_t b = get_event();
-    cudaEventRecord(b, s);
-    pending.push_back({open_name, open_ev, b});
-    open_ev = nullptr;
-  }
-  void collect() {
-    for (auto &p : pending) {
-      cudaEventSynchronize(p.b);
-      float ms = 0.f;
-      cudaEventElapsedTime(&ms, p.a, p.b);
-      bool found = false;
-      for (auto &t : totals)
-        if (t.first == p.name) { t.second.first += ms; t.second.second += 1; found = true; break; }
-      if (!found) totals.push_back({p.name, {ms, 1L}});
-      pool.push_back(p.a);
-      pool.push_back(p.b);
-    }
-    pending.clear();
+    prof_end(s);
   }
   ~rcu_rnn_s() {
-    for (auto &p : pending) { cudaEventDestroy(p.a); cudaEventDestroy(p.b); }
-    for (auto e : pool) cudaEventDestroy(e);
     for (auto e : chunk_ev) cudaEventDestroy(e);
     if (cp_in) cudaStreamDestroy(cp_in);
     if (cp_out) cudaStreamDestroy(cp_out);
@@ -1350,12 +1374,7 @@ extern "C" int rnn_last_launch_count(rcu_rnn_t h) { return h ? h->launches : -1;
 extern "C" int rnn_profile_entry(rcu_rnn_t h, int i, const char **name, double *total_ms,
                                  int64_t *count) {
   if (!h) return fail(RCU_ERR_INVALID, "rnn_profile_entry: NULL handle");
-  h->collect();
-  if (i < 0 || i >= (int)h->totals.size()) return fail(RCU_ERR_INVALID, "no profile entry %d", i);
-  if (name) *name = h->totals[i].first.c_str();
-  if (total_ms) *total_ms = h->totals[i].second.first;
-  if (count) *count = h->totals[i].second.second;
-  return RCU_OK;
+  return h->entry(i, name, total_ms, count);
 }
 
 extern "C" int rnn_get_trace(rcu_rnn_t h, int64_t *host_out, int n_steps, void *stream) {
@@ -1369,8 +1388,7 @@ extern "C" int rnn_get_trace(rcu_rnn_t h, int64_t *host_out, int n_steps, void *
 
 extern "C" int rnn_profile_reset(rcu_rnn_t h) {
   if (!h) return fail(RCU_ERR_INVALID, "rnn_profile_reset: NULL handle");
-  h->collect();
-  h->totals.clear();
+  h->reset();
   return RCU_OK;
 }
 
@@ -1384,7 +1402,7 @@ extern "C" int rnn_destroy(rcu_rnn_t h) {
 // ---------------------------------------------------------------------------
 // RSSM handle
 
-struct rcu_rssm_s {
+struct rcu_rssm_s : EventProfiler {
   int S, A, Hd, RH;
   int device, nsm;
   DevBuf W1, b1, Wih, Whh, bih, bhh, W2, b2, W3, b3;
@@ -1404,6 +1422,9 @@ struct rcu_rssm_s {
   // rssm_backward: workspace and the weight gradients of the last call
   DevBuf bw, gw;
   bool grads_ready = false;
+  // timed spans (RCU_ATTR_PROFILE); launches are counted by the callers
+  void begin(const char *name, cudaStream_t s) { prof_begin(name, s); }
+  void end(cudaStream_t s) { prof_end(s); }
 };
 
 extern "C" int rssm_set_attr(rcu_rssm_t h, int attr, int64_t value) {
@@ -1415,6 +1436,10 @@ extern "C" int rssm_set_attr(rcu_rssm_t h, int attr, int64_t value) {
   }
   if (attr == RCU_ATTR_TEST_DROP_ARRIVAL) {
     h->drop_send = value != 0;
+    return RCU_OK;
+  }
+  if (attr == RCU_ATTR_PROFILE) {
+    h->profile = value != 0;
     return RCU_OK;
   }
   if (attr != RCU_ATTR_TRACE) return fail(RCU_ERR_INVALID, "rssm_set_attr: unknown attribute %d", attr);
@@ -1539,7 +1564,9 @@ static int rssm_run(rcu_rssm_t h, bool with_actor, int T, int B, const float *st
     p.trace = (unsigned long long *)h->trace_buf.p;
   }
   int clusters = 0;
+  h->begin(with_actor ? "rssm_unroll_actor" : "rssm_unroll", (cudaStream_t)stream);
   cudaError_t e = launch_rssm(p, h->nsm, (cudaStream_t)stream, &clusters);
+  h->end((cudaStream_t)stream);
   if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rssm kernel launch: %s", cudaGetErrorString(e));
   h->launches = 1;
   return RCU_OK;
@@ -1678,6 +1705,7 @@ extern "C" int rssm_backward(rcu_rssm_t h, int T, int B, const float *state0,
     ++launches;
   };
   // ---- everything off the reverse-time chain, over all T*B rows
+  h->begin("rssm_bwd_recompute", s);
   if (e == cudaSuccess) e = launch_rssm_inputs(T, B, S, A, state0, states, actions, IN, s);
   ++launches;
   gemm(IN, SA, W1, SA, b1, U, Hd, M, Hd, SA);                    // u = W1 [s, a] + b1
@@ -1703,8 +1731,10 @@ extern "C" int rssm_backward(rcu_rssm_t h, int T, int B, const float *state0,
   tr(Wih, G, Hd, Hd, WihT, G);
   tr(W1, Hd, S, SA, W1sT, Hd);
   if (A > 0) tr(W1 + S, Hd, A, SA, W1aT, Hd);
+  h->end(s);
   if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rssm_backward: recompute: %s", cudaGetErrorString(e));
-  // ---- the reverse-time chain
+  // ---- the reverse-time chain (one timed span over all its launches)
+  h->begin("rssm_bwd_chain", s);
   CU(cudaMemsetAsync(GH, 0, (size_t)B * RH * 4, s));
   CU(cudaMemsetAsync(DHZ, 0, (size_t)B * RH * 4, s));
   CU(cudaMemsetAsync(CS, 0, (size_t)B * S * 4, s));
@@ -1725,7 +1755,9 @@ extern "C" int rssm_backward(rcu_rssm_t h, int T, int B, const float *state0,
     ++launches;
     gemm(DU + r0 * Hd, Hd, W1sT, Hd, nullptr, CS, S, B, S, Hd);       // ds_{t-1} part
   }
+  h->end(s);
   if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rssm_backward: recurrence: %s", cudaGetErrorString(e));
+  h->begin("rssm_bwd_grads", s);
   if (dstate0) CU(cudaMemcpyAsync(dstate0, CS, (size_t)B * S * 4, cudaMemcpyDeviceToDevice, s));
   if (dbelief0) {
     CU(cudaMemcpyAsync(dbelief0, GH, (size_t)B * RH * 4, cudaMemcpyDeviceToDevice, s));
@@ -1753,6 +1785,7 @@ extern "C" int rssm_backward(rcu_rssm_t h, int T, int B, const float *state0,
     if (e == cudaSuccess) e = launch_colsum(w.dz, M, w.nz, csum, w.db, s);
     launches += 2;
   }
+  h->end(s);
   if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rssm_backward: gradients: %s", cudaGetErrorString(e));
   h->grads_ready = true;
   h->launches = launches;
@@ -1775,6 +1808,18 @@ extern "C" int rssm_get_weight_grads(rcu_rssm_t h, float *dW1, float *db1, float
       CU(cudaMemcpyAsync(dst[i], src, nW[i] * 4, cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
     src += nW[i];
   }
+  return RCU_OK;
+}
+
+extern "C" int rssm_profile_entry(rcu_rssm_t h, int i, const char **name, double *total_ms,
+                                  int64_t *count) {
+  if (!h) return fail(RCU_ERR_INVALID, "rssm_profile_entry: NULL handle");
+  return h->entry(i, name, total_ms, count);
+}
+
+extern "C" int rssm_profile_reset(rcu_rssm_t h) {
+  if (!h) return fail(RCU_ERR_INVALID, "rssm_profile_reset: NULL handle");
+  h->reset();
   return RCU_OK;
 }
 

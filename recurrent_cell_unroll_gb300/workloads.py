@@ -6,7 +6,9 @@ take their inputs from here, so the two sides always see the same fp32 bits.
 
 All draws come from one CPU ``torch.Generator`` seeded per workload, in this
 order: for each layer, then direction: W_ih, W_hh, b_ih, b_hh, [W_hr]; then
-x; then lengths; then h0, c0; then (RSSM) actions and eps.  Weights and biases
+x; then lengths; then h0, c0; then (RSSM) actions and eps; the training
+workloads' output gradients come last, so every other draw stays that of the
+forward workload.  Weights and biases
 follow the PyTorch module default, U(-1/sqrt(hidden), 1/sqrt(hidden)); RSSM
 Linear layers use U(-1/sqrt(fan_in), 1/sqrt(fan_in)).
 
@@ -71,6 +73,9 @@ class RssmSpec:
     belief0_std: float = 0.0
     # unroll variant 2: actions from an actor of this hidden width (0 = given)
     actor_hidden: int = 0
+    # a training pass: the unroll and its backward pass through time given the
+    # gradients of the four outputs
+    train: bool = False
 
     def scaled(self, **kw) -> "RssmSpec":
         return dataclasses.replace(self, **kw)
@@ -79,6 +84,9 @@ class RssmSpec:
 LSTM_T80 = RnnSpec("lstm_f32_T80_B1_512x256", "lstm", 1, 512, 256, T=80, B=1)
 RSSM_B50 = RssmSpec("rssm_f32_B50_T50_S20_A6_H200", T=50, B=50)
 RSSM_ACTOR = RssmSpec("rssm_actor_f32_B50_T50_S20_A6_H200_X200", T=50, B=50, actor_hidden=200)
+# forward + backward through time of the given-actions unroll; the output
+# gradients dmeans, dstds, dstates, dbeliefs ~ N(0, 1)
+RSSM_TRAIN = RSSM_B50.scaled(name="rssm_train_f32_B50_T50_S20_A6_H200", train=True)
 LSTMP_2L = RnnSpec("lstmp_bf16_2L_T1000_B32_80x1024p256", "lstm", 2, 80, 1024, T=1000, B=32,
                    proj=256, dtype="bf16")
 BILSTM_VAR = RnnSpec("bilstm_f32_varlen_B64_T500_256x512", "lstm", 1, 256, 512, T=500, B=64,
@@ -94,7 +102,7 @@ LSTM_TRAIN = RnnSpec("lstm_train_f32_T500_B64_256x512", "lstm", 1, 256, 512, T=5
 BILSTM_TRAIN = BILSTM_VAR.scaled(name="bilstm_train_f32_varlen_B64_T500_256x512", train=True)
 
 WORKLOADS = {s.name: s for s in (LSTM_T80, RSSM_B50, LSTMP_2L, BILSTM_VAR, GRU_3L,
-                                  RSSM_ACTOR, LSTM_TRAIN, BILSTM_TRAIN)}
+                                  RSSM_ACTOR, LSTM_TRAIN, BILSTM_TRAIN, RSSM_TRAIN)}
 
 
 def _uniform(g, shape, bound):
@@ -160,6 +168,9 @@ def make_rssm_inputs(spec: RssmSpec, seed: int = 0) -> dict:
     if spec.belief0_std > 0:
         belief0 = torch.randn((spec.B, RH), generator=g, dtype=torch.float32) * spec.belief0_std
     out = {"weights": w, "actions": actions, "eps": eps, "state0": state0, "belief0": belief0}
+    if spec.train:  # drawn last: the other draws stay those of the forward workload
+        for k, n in (("dmeans", S), ("dstds", S), ("dstates", S), ("dbeliefs", RH)):
+            out[k] = torch.randn((spec.T, spec.B, n), generator=g, dtype=torch.float32)
     if spec.actor_hidden:
         out["actions"] = None
         out["actor"] = make_rssm_actor(spec, seed, spec.actor_hidden)

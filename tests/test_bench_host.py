@@ -143,6 +143,28 @@ def test_bidirectional_varlen_training_flops():
     assert inp["dy"].shape == (6, 3, 2 * H)
 
 
+def test_rssm_training_flops_and_draws():
+    """RSSM training pass: one FLOP entry per timed phase of rssm_backward (the
+    unroll, the recompute, the reverse-time chain, the gradients), and the
+    output-gradient draws leave the forward workload's inputs unchanged."""
+    spec = wl.RSSM_TRAIN.scaled(T=3, B=2)
+    inp = wl.make_rssm_inputs(spec, seed=2)
+    fwd = wl.make_rssm_inputs(spec.scaled(train=False), seed=2)
+    for k in ("actions", "eps"):
+        assert torch.equal(inp[k], fwd[k])
+    S, A, Hd, RH = spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden
+    for k, n in (("dmeans", S), ("dstds", S), ("dstates", S), ("dbeliefs", RH)):
+        assert inp[k].shape == (3, 2, n)
+    fl = bench.kernel_flops(spec, inp)
+    rs = 6
+    prior = 2 * (Hd * (S + A) + 3 * RH * Hd + 3 * RH * RH + Hd * RH + 2 * S * Hd)
+    assert fl == {"rssm_unroll": [prior * rs], "rssm_bwd_recompute": [prior * rs],
+                  "rssm_bwd_chain": [2 * (3 * S * Hd + Hd * RH + 3 * RH * RH + 3 * RH * Hd)
+                                     * rs],
+                  "rssm_bwd_grads": [(prior + 2 * A * Hd) * rs]}
+    assert bench.oracle_serial(spec) and not bench.oracle_serial(wl.RSSM_B50)
+
+
 def test_traffic_table_names_real_workloads_and_kernels():
     """Every captured traffic entry belongs to a bench workload and to a kernel
     name the roofline can report for it."""

@@ -969,6 +969,26 @@ def test_rssm_backward_parity(spec, which):
     m.close()
 
 
+def test_rssm_profile_phases():
+    """RCU_ATTR_PROFILE on an RSSM handle times the unroll and the three phases
+    of rssm_backward, once per call each."""
+    spec = wl.RSSM_B50.scaled(T=5, B=4)
+    inp = wl.make_rssm_inputs(spec, seed=23)
+    dev = torch.device("cuda")
+    m = binding.RSSM(spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden)
+    m.set_weights(inp["weights"])
+    m.set_attr(binding.RCU_ATTR_PROFILE, 1)
+    binding.rssm_profile_reset(m.h)
+    m.backward(inp["actions"].to(dev), inp["eps"].to(dev),
+               dbeliefs=torch.ones((spec.T, spec.B, spec.rnn_hidden), device=dev))
+    prof = m.profile()
+    assert binding.rssm_get_status(m.h) == 0
+    for name in ("rssm_unroll", "rssm_bwd_recompute", "rssm_bwd_chain", "rssm_bwd_grads"):
+        assert name in prof and prof[name][1] == 1 and prof[name][0] > 0.0, (name, prof)
+    assert m.launch_count() > 4 * spec.T
+    m.close()
+
+
 # ----------------------------------------------------------------------------- full-size training pass
 
 @pytest.mark.parametrize("spec", [wl.LSTM_TRAIN, wl.BILSTM_TRAIN], ids=lambda s: s.name)
