@@ -68,6 +68,8 @@ def _load():
             lib.oracle_rnn_backward.argtypes = [i] * 9 + [P] * 16 + [i]
             lib.oracle_rssm_backward.restype = i
             lib.oracle_rssm_backward.argtypes = [i] * 6 + [P] * 31
+            lib.oracle_rssm_backward2.restype = i
+            lib.oracle_rssm_backward2.argtypes = [i] * 6 + [P] * 31 + [i] + [P] * 8
             lib.oracle_bf16_round.restype = ctypes.c_double
             lib.oracle_bf16_round.argtypes = [ctypes.c_float]
             lib.oracle_num_threads_default.restype = i
@@ -268,19 +270,24 @@ RSSM_WEIGHTS = ("W1", "b1", "W_ih", "W_hh", "b_ih", "b_hh", "W2", "b2", "W3", "b
 
 
 def rssm_backward(weights, actions, eps, *, state0=None, belief0=None, dmeans=None, dstds=None,
-                  dstates=None, dbeliefs=None):
-    """Backward pass through time of the RSSM prior unroll with given actions
-    (rssm_unroll), in fp64: the gradients of a loss whose gradient with
-    respect to the outputs is dmeans, dstds, dstates [T,B,S] and dbeliefs
-    [T,B,RH] (None = 0).  Returns a dict: dstate0 [B,S], dbelief0 [B,RH],
-    dactions [T,B,A] and d<name> for every weight and bias of rssm_unroll's
-    dict, in its shape.  eps is an input (the noise), not differentiated.
+                  dstates=None, dbeliefs=None, actor=None):
+    """Backward pass through time of the RSSM prior unroll in fp64: the
+    gradients of a loss whose gradient with respect to the outputs is
+    dmeans, dstds, dstates [T,B,S] and dbeliefs [T,B,RH] (None = 0).
+    Returns a dict: dstate0 [B,S], dbelief0 [B,RH], dactions [T,B,A] and
+    d<name> for every weight and bias of rssm_unroll's dict, in its shape.
+    eps is an input (the noise), not differentiated.
+
+    With actor (the dict of rssm_unroll_actor) the unroll is variant 2:
+    actions is ignored (may be None), dactions is the gradient reaching each
+    action the actor produced, and dWa1, dba1, dWa2, dba2 are added.
     """
     lib = _load()
-    a = _f32(actions)
+    a = None if actor is not None else _f32(actions)
     e = _f32(eps)
     T, B, S = e.shape
-    A = a.shape[2] if a is not None else 0
+    Ac = {k: _f32(v) for k, v in actor.items()} if actor is not None else None
+    A = Ac["Wa2"].shape[0] if Ac is not None else (a.shape[2] if a is not None else 0)
     W = {k: _f32(weights.get(k)) for k in RSSM_WEIGHTS}
     Hd = W["W1"].shape[0]
     RH = W["W_hh"].shape[1]
@@ -293,10 +300,18 @@ def rssm_backward(weights, actions, eps, *, state0=None, belief0=None, dmeans=No
            "dactions": np.zeros((T, B, A))}
     for k in RSSM_WEIGHTS:
         out["d" + k] = np.zeros(shapes[k])
-    rc = lib.oracle_rssm_backward(
+    Ha = 0
+    actor_args = [None] * 8
+    if Ac is not None:
+        Ha = Ac["Wa1"].shape[0]
+        for k, shp in (("Wa1", (Ha, S + RH)), ("ba1", (Ha,)), ("Wa2", (A, Ha)), ("ba2", (A,))):
+            out["d" + k] = np.zeros(shp)
+        actor_args = [_ptr(Ac["Wa1"]), _ptr(Ac.get("ba1")), _ptr(Ac["Wa2"]), _ptr(Ac.get("ba2")),
+                      _ptr(out["dWa1"]), _ptr(out["dba1"]), _ptr(out["dWa2"]), _ptr(out["dba2"])]
+    rc = lib.oracle_rssm_backward2(
         S, A, Hd, RH, T, B, *[_ptr(W[k]) for k in RSSM_WEIGHTS], _ptr(s0), _ptr(b0), _ptr(a),
         _ptr(e), *[_ptr(v) for v in g_in], _ptr(out["dstate0"]), _ptr(out["dbelief0"]),
-        _ptr(out["dactions"]), *[_ptr(out["d" + k]) for k in RSSM_WEIGHTS])
+        _ptr(out["dactions"]), *[_ptr(out["d" + k]) for k in RSSM_WEIGHTS], Ha, *actor_args)
     if rc != 0:
         raise ValueError("oracle_rssm_backward: invalid arguments")
     return out

@@ -794,21 +794,45 @@ int oracle_rnn_backward(int cell, int bidir, int layers, int in_dim, int hidden,
 /* and the chain rule through these, taken in reverse time, is written out  */
 /* term by term below.  Rows are processed one after another (the weight   */
 /* gradients sum over all of them).                                          */
+/*                                                                          */
+/* oracle_rssm_backward2 is the same for the second unroll variant (the     */
+/* same issue's Solution, actions computed on the fly): with an actor       */
+/* (Wa1 non-NULL) the action of step t is                                    */
+/*   a_t = tanh(Wa2 ELU(Wa1 [s_{t-1}, h_{t-1}] + ba1) + ba2)                 */
+/* as in oracle_rssm_unroll2, `actions` is not read, dactions[t] is the     */
+/* gradient reaching a_t, and the actor's gradients dWa1 [Ha, S+RH], dba1,  */
+/* dWa2 [A, Ha], dba2 are returned; its input path adds to the gradients   */
+/* of s_{t-1} and h_{t-1}.                                                   */
 /* ---------------------------------------------------------------------- */
 static double elu_grad(double u) { return u > 0.0 ? 1.0 : exp(u); }
 
-int oracle_rssm_backward(int S, int A, int Hd, int RH, int T, int B, const float *W1,
-                         const float *b1, const float *Wih, const float *Whh, const float *bih,
-                         const float *bhh, const float *W2, const float *b2, const float *W3,
-                         const float *b3, const float *state0, const float *belief0,
-                         const float *actions, const float *eps, const float *dmeans,
-                         const float *dstds, const float *dstates, const float *dbeliefs,
-                         double *dstate0, double *dbelief0, double *dactions, double *dW1,
-                         double *db1, double *dWih, double *dWhh, double *dbih, double *dbhh,
-                         double *dW2, double *db2, double *dW3, double *db3) {
+int oracle_rssm_backward2(int S, int A, int Hd, int RH, int T, int B, const float *W1,
+                          const float *b1, const float *Wih, const float *Whh, const float *bih,
+                          const float *bhh, const float *W2, const float *b2, const float *W3,
+                          const float *b3, const float *state0, const float *belief0,
+                          const float *actions, const float *eps, const float *dmeans,
+                          const float *dstds, const float *dstates, const float *dbeliefs,
+                          double *dstate0, double *dbelief0, double *dactions, double *dW1,
+                          double *db1, double *dWih, double *dWhh, double *dbih, double *dbhh,
+                          double *dW2, double *db2, double *dW3, double *db3, int Ha,
+                          const float *Wa1, const float *ba1, const float *Wa2, const float *ba2,
+                          double *dWa1, double *dba1, double *dWa2, double *dba2) {
     if (S < 1 || A < 0 || Hd < 1 || RH < 1 || T < 0 || B < 0) return -1;
-    if ((A > 0 && !actions) || !eps) return -1;
-    const int SA = S + A, G = 3 * RH;
+    const int actor = Wa1 != NULL;
+    if (actor && (Ha < 1 || !Wa2 || A < 1 || !dWa1 || !dba1 || !dWa2 || !dba2)) return -1;
+    if ((!actor && A > 0 && !actions) || !eps) return -1;
+    const int SA = S + A, G = 3 * RH, SR = S + RH;
+    const int Hn = actor ? Ha : 1;
+    double *wa1 = actor ? widen(Wa1, (size_t)Ha * SR, 0) : NULL;
+    double *vba1 = actor ? widen(ba1, Ha, 0) : NULL;
+    double *wa2 = actor ? widen(Wa2, (size_t)A * Ha, 0) : NULL;
+    double *vba2 = actor ? widen(ba2, A, 0) : NULL;
+    if (actor) {
+        memset(dWa1, 0, (size_t)Ha * SR * sizeof(double));
+        memset(dba1, 0, (size_t)Ha * sizeof(double));
+        memset(dWa2, 0, (size_t)A * Ha * sizeof(double));
+        memset(dba2, 0, (size_t)A * sizeof(double));
+    }
     double *w1 = widen(W1, (size_t)Hd * SA, 0), *vb1 = widen(b1, Hd, 0);
     double *wih = widen(Wih, (size_t)G * Hd, 0), *whh = widen(Whh, (size_t)G * RH, 0);
     double *vbih = widen(bih, G, 0), *vbhh = widen(bhh, G, 0);
@@ -836,6 +860,10 @@ int oracle_rssm_backward(int S, int A, int Hd, int RH, int T, int B, const float
     double *v_s = (double *)calloc(Tn * Hd, sizeof(double));
     double *q_s = (double *)calloc(Tn * Hd, sizeof(double));
     double *p_s = (double *)calloc(Tn * 2 * S, sizeof(double));
+    double *ua_s = (double *)calloc(Tn * Hn, sizeof(double));   /* actor pre-ELU */
+    double *ha_s = (double *)calloc(Tn * Hn, sizeof(double));   /* actor hidden layer */
+    double *dha = (double *)calloc((size_t)Hn, sizeof(double));
+    double *dva = (double *)calloc((size_t)(A > 0 ? A : 1), sizeof(double));
     double *gs = (double *)calloc((size_t)S, sizeof(double));    /* dL/ds_t from step t+1 */
     double *gh = (double *)calloc((size_t)RH, sizeof(double));   /* dL/dh_t from step t+1 */
     double *ngs = (double *)calloc((size_t)S, sizeof(double));
@@ -855,7 +883,24 @@ int oracle_rssm_backward(int S, int A, int Hd, int RH, int T, int B, const float
         for (int t = 0; t < T; ++t) {
             double *in = in_s + (size_t)t * SA;
             for (int j = 0; j < S; ++j) in[j] = st[j];
-            for (int j = 0; j < A; ++j) in[S + j] = (double)actions[((size_t)t * B + b) * A + j];
+            if (actor) {
+                /* a_t = tanh(Wa2 ELU(Wa1 [s_{t-1}, h_{t-1}] + ba1) + ba2) */
+                double *ua = ua_s + (size_t)t * Ha, *ha = ha_s + (size_t)t * Ha;
+                for (int i = 0; i < Ha; ++i) {
+                    double u = vba1 ? vba1[i] : 0.0;
+                    for (int j = 0; j < S; ++j) u += wa1[(size_t)i * SR + j] * st[j];
+                    for (int j = 0; j < RH; ++j) u += wa1[(size_t)i * SR + S + j] * bel[j];
+                    ua[i] = u;
+                    ha[i] = elu(u);
+                }
+                for (int j = 0; j < A; ++j) {
+                    double v = vba2 ? vba2[j] : 0.0;
+                    for (int i = 0; i < Ha; ++i) v += wa2[(size_t)j * Ha + i] * ha[i];
+                    in[S + j] = tanh(v);
+                }
+            } else {
+                for (int j = 0; j < A; ++j) in[S + j] = (double)actions[((size_t)t * B + b) * A + j];
+            }
             for (int i = 0; i < Hd; ++i) {
                 double u = vb1 ? vb1[i] : 0.0;
                 for (int j = 0; j < SA; ++j) u += w1[(size_t)i * SA + j] * in[j];
@@ -968,7 +1013,33 @@ int oracle_rssm_backward(int S, int A, int Hd, int RH, int T, int B, const float
                 double a = 0.0;
                 for (int i = 0; i < Hd; ++i) a += w1[(size_t)i * SA + j] * du[i];
                 if (j < S) ngs[j] = a;
-                else if (dactions) dactions[o * A + (j - S)] = a;
+                else {
+                    if (dactions) dactions[o * A + (j - S)] = a;
+                    /* actor: the action's gradient through tanh */
+                    if (actor) dva[j - S] = a * (1.0 - in[j] * in[j]);
+                }
+            }
+            if (actor) {
+                /* actor: a = tanh(Wa2 ha + ba2), ha = ELU(ua), ua = Wa1 [s_{t-1}, h_{t-1}] + ba1 */
+                const double *ua = ua_s + (size_t)t * Ha, *ha = ha_s + (size_t)t * Ha;
+                for (int j = 0; j < A; ++j) {
+                    dba2[j] += dva[j];
+                    for (int i = 0; i < Ha; ++i) dWa2[(size_t)j * Ha + i] += dva[j] * ha[i];
+                }
+                for (int i = 0; i < Ha; ++i) {
+                    double a = 0.0;
+                    for (int j = 0; j < A; ++j) a += wa2[(size_t)j * Ha + i] * dva[j];
+                    dha[i] = a * elu_grad(ua[i]);
+                }
+                for (int i = 0; i < Ha; ++i) {
+                    dba1[i] += dha[i];
+                    for (int j = 0; j < S; ++j) dWa1[(size_t)i * SR + j] += dha[i] * in[j];
+                    for (int j = 0; j < RH; ++j) dWa1[(size_t)i * SR + S + j] += dha[i] * hp[j];
+                }
+                for (int j = 0; j < S; ++j)
+                    for (int i = 0; i < Ha; ++i) ngs[j] += wa1[(size_t)i * SR + j] * dha[i];
+                for (int j = 0; j < RH; ++j)
+                    for (int i = 0; i < Ha; ++i) ngh[j] += wa1[(size_t)i * SR + S + j] * dha[i];
             }
             memcpy(gs, ngs, (size_t)S * sizeof(double));
             memcpy(gh, ngh, (size_t)RH * sizeof(double));
@@ -979,7 +1050,25 @@ int oracle_rssm_backward(int S, int A, int Hd, int RH, int T, int B, const float
     free(in_s); free(u_s); free(x_s); free(hp_s); free(g_s); free(hn_s); free(h_s);
     free(v_s); free(q_s); free(p_s); free(gs); free(gh); free(ngs); free(ngh); free(dp);
     free(dv); free(dh); free(din); free(dhid); free(du); free(st); free(bel);
+    free(ua_s); free(ha_s); free(dha); free(dva);
     free(w1); free(vb1); free(wih); free(whh); free(vbih); free(vbhh);
     free(w2); free(vb2); free(w3); free(vb3);
+    free(wa1); free(vba1); free(wa2); free(vba2);
     return 0;
+}
+
+int oracle_rssm_backward(int S, int A, int Hd, int RH, int T, int B, const float *W1,
+                         const float *b1, const float *Wih, const float *Whh, const float *bih,
+                         const float *bhh, const float *W2, const float *b2, const float *W3,
+                         const float *b3, const float *state0, const float *belief0,
+                         const float *actions, const float *eps, const float *dmeans,
+                         const float *dstds, const float *dstates, const float *dbeliefs,
+                         double *dstate0, double *dbelief0, double *dactions, double *dW1,
+                         double *db1, double *dWih, double *dWhh, double *dbih, double *dbhh,
+                         double *dW2, double *db2, double *dW3, double *db3) {
+    return oracle_rssm_backward2(S, A, Hd, RH, T, B, W1, b1, Wih, Whh, bih, bhh, W2, b2, W3, b3,
+                                 state0, belief0, actions, eps, dmeans, dstds, dstates, dbeliefs,
+                                 dstate0, dbelief0, dactions, dW1, db1, dWih, dWhh, dbih, dbhh,
+                                 dW2, db2, dW3, db3, 0, NULL, NULL, NULL, NULL, NULL, NULL, NULL,
+                                 NULL);
 }

@@ -1116,3 +1116,117 @@ def test_rssm_backward_head_only_closed_form():
     np.testing.assert_allclose(g["db3"][:S], gr["dmeans"][0].astype(np.float64).sum(0),
                                rtol=1e-12, atol=1e-12)
     assert np.all(g["db3"][S:] == 0.0)
+
+
+def _rssm_actor_case(seed, T=5, B=3, S=4, A=3, Hd=6, RH=5, Ha=7):
+    w, _, eps, s0, b0, gr = _rssm_case(seed, T=T, B=B, S=S, A=A, Hd=Hd, RH=RH)
+    rng = np.random.default_rng(seed + 1)
+    u = lambda shape, fan: (rng.uniform(-1, 1, shape) / np.sqrt(fan)).astype(np.float32)
+    actor = {"Wa1": u((Ha, S + RH), S + RH), "ba1": u((Ha,), S + RH),
+             "Wa2": u((A, Ha), Ha), "ba2": u((A,), Ha)}
+    return w, actor, eps, s0, b0, gr
+
+
+def test_rssm_actor_backward_against_torch_autograd():
+    """Unroll variant 2 (the actor in the loop): the oracle's gradients equal
+    torch float64 autograd through the actor (Linear, ELU, Linear, Tanh on
+    [state, belief]) and the prior modules, for state0, belief0, every prior
+    weight, every actor weight and each produced action."""
+    w, actor, eps, s0, b0, gr = _rssm_actor_case(51)
+    T, B, S = eps.shape
+    Hd, RH = w["W1"].shape[0], w["W_hh"].shape[1]
+    A, Ha = actor["Wa2"].shape
+    g = oracle.rssm_backward(w, None, eps, state0=s0, belief0=b0, actor=actor, **gr)
+    d = lambda a: torch.from_numpy(np.asarray(a)).double()
+    lin1 = torch.nn.Linear(S + A, Hd, dtype=torch.float64)
+    gru = torch.nn.GRUCell(Hd, RH, dtype=torch.float64)
+    lin2 = torch.nn.Linear(RH, Hd, dtype=torch.float64)
+    lin3 = torch.nn.Linear(Hd, 2 * S, dtype=torch.float64)
+    act1 = torch.nn.Linear(S + RH, Ha, dtype=torch.float64)
+    act2 = torch.nn.Linear(Ha, A, dtype=torch.float64)
+    params = {"W1": lin1.weight, "b1": lin1.bias, "W_ih": gru.weight_ih, "W_hh": gru.weight_hh,
+              "b_ih": gru.bias_ih, "b_hh": gru.bias_hh, "W2": lin2.weight, "b2": lin2.bias,
+              "W3": lin3.weight, "b3": lin3.bias, "Wa1": act1.weight, "ba1": act1.bias,
+              "Wa2": act2.weight, "ba2": act2.bias}
+    with torch.no_grad():
+        for k, prm in params.items():
+            prm.copy_(d(w[k] if k in w else actor[k]))
+    st0, bl0 = d(s0).requires_grad_(), d(b0).requires_grad_()
+    state, belief = st0, bl0
+    loss = torch.zeros((), dtype=torch.float64)
+    acts = []
+    for t in range(T):
+        action = torch.tanh(act2(torch.nn.functional.elu(act1(torch.cat([state, belief], -1)))))
+        action.retain_grad()
+        acts.append(action)
+        x = torch.nn.functional.elu(lin1(torch.cat([state, action], dim=-1)))
+        belief = gru(x, belief)
+        p = lin3(torch.nn.functional.elu(lin2(belief)))
+        mean = p[:, :S]
+        std = torch.nn.functional.softplus(p[:, S:]) + 0.1
+        state = mean + d(eps[t]) * std
+        loss = loss + (mean * d(gr["dmeans"][t])).sum() + (std * d(gr["dstds"][t])).sum() \
+            + (state * d(gr["dstates"][t])).sum() + (belief * d(gr["dbeliefs"][t])).sum()
+    loss.backward()
+    tol = dict(rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(g["dstate0"], st0.grad.numpy(), **tol)
+    np.testing.assert_allclose(g["dbelief0"], bl0.grad.numpy(), **tol)
+    np.testing.assert_allclose(g["dactions"], torch.stack([a.grad for a in acts]).numpy(), **tol)
+    for k, prm in params.items():
+        np.testing.assert_allclose(g["d" + k], prm.grad.numpy(), **tol, err_msg=k)
+
+
+def test_rssm_actor_backward_finite_differences():
+    """Central differences of the (separately pinned) oracle actor unroll agree
+    with the oracle's actor-variant backward for state0, belief0 and every
+    actor weight and bias."""
+    w, actor, eps, s0, b0, gr = _rssm_actor_case(53, T=4, B=2)
+    g = oracle.rssm_backward(w, None, eps, state0=s0, belief0=b0, actor=actor, **gr)
+
+    def loss(ac, s_, b_):
+        m, sd, st, bl, _ = oracle.rssm_unroll_actor(w, ac, eps, state0=s_, belief0=b_)
+        return float((m * gr["dmeans"]).sum() + (sd * gr["dstds"]).sum()
+                     + (st * gr["dstates"]).sum() + (bl * gr["dbeliefs"]).sum())
+
+    h = np.float32(2.0 ** -14)
+    rng = np.random.default_rng(10)
+
+    def check(arr, grad, rebuild):
+        for _ in range(3):
+            idx = tuple(int(rng.integers(0, n)) for n in arr.shape)
+            hi, lo = arr.copy(), arr.copy()
+            hi[idx] += h
+            lo[idx] -= h
+            fd = (loss(*rebuild(hi)) - loss(*rebuild(lo))) / (2 * float(h))
+            assert abs(fd - grad[idx]) <= 1e-5 * max(1.0, abs(grad[idx])), (idx, fd, grad[idx])
+
+    check(s0, g["dstate0"], lambda a: (actor, a, b0))
+    check(b0, g["dbelief0"], lambda a: (actor, s0, a))
+    for k in ("Wa1", "ba1", "Wa2", "ba2"):
+        def rebuild(a, k=k):
+            ac = dict(actor)
+            ac[k] = a
+            return ac, s0, b0
+        check(actor[k], g["d" + k], rebuild)
+
+
+def test_rssm_constant_actor_backward_reduces_to_given_actions():
+    """Zero actor weights with ba2 = atanh(v) act v whatever the state: the
+    prior's gradients equal the given-actions backward with actions = v, no
+    gradient reaches Wa1 or ba1 (Wa2 = 0 stops it), and dba2 = (1 - v^2) times
+    the summed action gradients."""
+    w, _, eps, s0, b0, gr = _rssm_case(57, T=5, B=3, A=2)
+    v = np.array([0.3, -0.6], np.float32)
+    Ha, S, RH = 4, eps.shape[2], w["W_hh"].shape[1]
+    actor = {"Wa1": np.zeros((Ha, S + RH), np.float32), "ba1": np.ones(Ha, np.float32),
+             "Wa2": np.zeros((2, Ha), np.float32),
+             "ba2": np.arctanh(v.astype(np.float64)).astype(np.float32)}
+    got = oracle.rssm_backward(w, None, eps, state0=s0, belief0=b0, actor=actor, **gr)
+    acts = np.tanh(actor["ba2"].astype(np.float64))
+    ref = oracle.rssm_backward(w, np.broadcast_to(acts, (5, 3, 2)).astype(np.float32), eps,
+                               state0=s0, belief0=b0, **gr)
+    for k in ["dstate0", "dbelief0", "dactions"] + ["d" + n for n in oracle.RSSM_WEIGHTS]:
+        np.testing.assert_allclose(got[k], ref[k], rtol=1e-6, atol=1e-6, err_msg=k)
+    assert np.all(got["dWa1"] == 0.0) and np.all(got["dba1"] == 0.0)
+    np.testing.assert_allclose(got["dba2"], (1 - acts ** 2) * got["dactions"].sum((0, 1)),
+                               rtol=1e-12, atol=1e-12)
