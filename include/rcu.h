@@ -432,6 +432,30 @@ RCU_API int rssm_backward(rcu_rssm_t h, int T, int B, const float *state0, const
                           float *dstate0, float *dbelief0, float *dactions, void *stream);
 
 /*
+ * Backward pass through time of rssm_unroll_actor (unroll variant 2: the
+ * actions come from the actor set by rssm_set_actor, computed from the
+ * state and belief before each step).  As rssm_backward, without actions:
+ * dactions [T, B, A] (or NULL) receives the gradient reaching each action
+ * the actor produced, the prior's weight gradients are read with
+ * rssm_get_weight_grads and the actor's with rssm_get_actor_grads; the
+ * actor's input path adds to the gradients of the previous state and
+ * belief.  RCU_ERR_STATE without an actor.
+ */
+RCU_API int rssm_backward_actor(rcu_rssm_t h, int T, int B, const float *state0,
+                                const float *belief0, const float *eps, const float *dmeans,
+                                const float *dstds, const float *dstates, const float *dbeliefs,
+                                float *dstate0, float *dbelief0, float *dactions, void *stream);
+
+/*
+ * The actor's weight gradients from the last rssm_backward_actor, in
+ * rssm_set_actor's layouts: dWa1 [Ha, S+RH], dba1 [Ha], dWa2 [A, Ha], dba2
+ * [A]; device, any may be NULL.  RCU_ERR_STATE when the last backward had no
+ * actor.
+ */
+RCU_API int rssm_get_actor_grads(rcu_rssm_t h, float *dWa1, float *dba1, float *dWa2,
+                                 float *dba2, void *stream);
+
+/*
  * Weight gradients of the last rssm_backward in rssm_set_weights' layouts:
  * dW1 [Hd, S+A], db1 [Hd], dW_ih [3RH, Hd], dW_hh [3RH, RH], db_ih, db_hh
  * [3RH], dW2 [Hd, RH], db2 [Hd], dW3 [2S, Hd], db3 [2S]; device, any may be

@@ -40,7 +40,8 @@ EXPORTED = (
     "rssm_last_launch_count", "rssm_destroy", "rssm_set_attr", "rssm_get_trace",
     "rssm_set_actor", "rssm_unroll_actor", "rnn_forward_host", "rssm_unroll_host",
     "rssm_unroll_actor_host", "rnn_backward", "rnn_get_weight_grads", "rssm_backward",
-    "rssm_get_weight_grads", "rssm_profile_entry", "rssm_profile_reset",
+    "rssm_get_weight_grads", "rssm_profile_entry", "rssm_profile_reset", "rssm_backward_actor",
+    "rssm_get_actor_grads",
 )
 
 _lib = None
@@ -103,6 +104,8 @@ def load(path: Optional[str] = None):
             "rssm_unroll_actor_host": (I, [P, I, I] + [P] * 8 + [P]),
             "rssm_backward": (I, [P, I, I] + [P] * 12),
             "rssm_get_weight_grads": (I, [P] + [P] * 11),
+            "rssm_backward_actor": (I, [P, I, I] + [P] * 11),
+            "rssm_get_actor_grads": (I, [P] * 6),
             "rssm_profile_entry": (I, [P, I, ctypes.POINTER(ctypes.c_char_p),
                                        ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64)]),
             "rssm_profile_reset": (I, [P]),
@@ -323,6 +326,25 @@ def rssm_backward(h, T: int, B: int, state0, belief0, actions, eps, dmeans, dstd
                                 _stream(stream)))
 
 
+def rssm_backward_actor(h, T: int, B: int, state0, belief0, eps, dmeans, dstds, dstates,
+                        dbeliefs, dstate0, dbelief0, dactions, stream=None):
+    """Backward pass through time of rssm_unroll_actor (see rcu.h); device tensors."""
+    ins = [_dev(t) for t in (state0, belief0, eps, dmeans, dstds, dstates, dbeliefs)]
+    outs = [_dev(t) for t in (dstate0, dbelief0, dactions)]
+    _check(load().rssm_backward_actor(h, T, B, *[k[1] for k in ins], *[k[1] for k in outs],
+                                      _stream(stream)))
+
+
+RSSM_ACTOR_NAMES = ("Wa1", "ba1", "Wa2", "ba2")
+
+
+def rssm_get_actor_grads(h, grads: dict, stream=None):
+    """Copy the last rssm_backward_actor's actor gradients into the device
+    tensors of grads (keys of RSSM_ACTOR_NAMES; missing or None are skipped)."""
+    outs = [_dev(grads.get(k)) for k in RSSM_ACTOR_NAMES]
+    _check(load().rssm_get_actor_grads(h, *[k[1] for k in outs], _stream(stream)))
+
+
 RSSM_WEIGHT_NAMES = ("W1", "b1", "W_ih", "W_hh", "b_ih", "b_hh", "W2", "b2", "W3", "b3")
 
 
@@ -493,6 +515,7 @@ class RSSM:
 
     def __init__(self, state_dim: int, action_dim: int, hidden: int, rnn_hidden: int):
         self.S, self.A, self.Hd, self.RH = state_dim, action_dim, hidden, rnn_hidden
+        self.Ha = 0  # actor width once set_actor has run
         self.h = rssm_create(state_dim, action_dim, hidden, rnn_hidden)
 
     def set_weights(self, w, device="cuda", stream=None):
@@ -532,6 +555,29 @@ class RSSM:
         rssm_get_weight_grads(self.h, grads, stream)
         return dstate0, dbelief0, dactions, grads
 
+    def backward_actor(self, eps, state0=None, belief0=None, dmeans=None, dstds=None,
+                       dstates=None, dbeliefs=None, stream=None):
+        """Backward pass of unroll_actor: returns (dstate0, dbelief0, dactions
+        (the gradient reaching each produced action), dict of the prior's
+        weight gradients, dict of the actor's: Wa1, ba1, Wa2, ba2)."""
+        T, B, _ = eps.shape
+        dev = eps.device
+        dstate0 = torch.empty((B, self.S), device=dev)
+        dbelief0 = torch.empty((B, self.RH), device=dev)
+        dactions = torch.empty((T, B, self.A), device=dev)
+        rssm_backward_actor(self.h, T, B, state0, belief0, eps, dmeans, dstds, dstates, dbeliefs,
+                            dstate0, dbelief0, dactions, stream)
+        S, A, Hd, RH, Ha = self.S, self.A, self.Hd, self.RH, self.Ha
+        shapes = {"W1": (Hd, S + A), "b1": (Hd,), "W_ih": (3 * RH, Hd), "W_hh": (3 * RH, RH),
+                  "b_ih": (3 * RH,), "b_hh": (3 * RH,), "W2": (Hd, RH), "b2": (Hd,),
+                  "W3": (2 * S, Hd), "b3": (2 * S,)}
+        grads = {k: torch.empty(shapes[k], device=dev) for k in RSSM_WEIGHT_NAMES}
+        rssm_get_weight_grads(self.h, grads, stream)
+        ashapes = {"Wa1": (Ha, S + RH), "ba1": (Ha,), "Wa2": (A, Ha), "ba2": (A,)}
+        agrads = {k: torch.empty(ashapes[k], device=dev) for k in RSSM_ACTOR_NAMES}
+        rssm_get_actor_grads(self.h, agrads, stream)
+        return dstate0, dbelief0, dactions, grads, agrads
+
     def set_actor(self, a, device="cuda", stream=None):
         """Actor of the second unroll variant: dict Wa1 [Ha, S+RH], ba1 [Ha],
         Wa2 [A, Ha], ba2 [A] (biases may be None)."""
@@ -539,6 +585,7 @@ class RSSM:
              for k, v in a.items()}
         rssm_set_actor(self.h, t["Wa1"].shape[0], t["Wa1"], t.get("ba1"), t["Wa2"],
                        t.get("ba2"), stream)
+        self.Ha = t["Wa1"].shape[0]
 
     def unroll_actor(self, eps, state0=None, belief0=None, stream=None):
         """Unroll over eps' T steps with the actions computed by the actor;

@@ -1419,9 +1419,10 @@ struct rcu_rssm_s : EventProfiler {
   int trace_T = 0;
   // rssm_unroll_host / rssm_unroll_actor_host staging buffers
   DevBuf io_s0, io_b0, io_act, io_eps, io_out[5];
-  // rssm_backward: workspace and the weight gradients of the last call
-  DevBuf bw, gw;
-  bool grads_ready = false;
+  // rssm_backward: workspace and the weight gradients of the last call (gwa:
+  // the actor's, after rssm_backward_actor)
+  DevBuf bw, gw, gwa;
+  bool grads_ready = false, actor_grads_ready = false;
   // timed spans (RCU_ATTR_PROFILE); launches are counted by the callers
   void begin(const char *name, cudaStream_t s) { prof_begin(name, s); }
   void end(cudaStream_t s) { prof_end(s); }
@@ -1637,7 +1638,11 @@ extern "C" int rssm_unroll_actor_host(rcu_rssm_t h, int T, int B, const float *s
 // the same activation scan as the stacked-RNN backward); the chain runs one
 // step at a time as five batched mat-vecs between elementwise kernels; the
 // weight and action gradients are GEMMs over all rows afterwards.
-extern "C" int rssm_backward(rcu_rssm_t h, int T, int B, const float *state0,
+// With the actor (unroll variant 2) the actions are the forward's own: the
+// actor's layers are recomputed over all rows like the prior's, and each step
+// of the chain also takes the gradient reaching a_t back through tanh, Wa2,
+// ELU and Wa1 into s_{t-1} and h_{t-1}.
+static int rssm_backward_run(rcu_rssm_t h, bool with_actor, int T, int B, const float *state0,
                              const float *belief0, const float *actions, const float *eps,
                              const float *dmeans, const float *dstds, const float *dstates,
                              const float *dbeliefs, float *dstate0, float *dbelief0,
@@ -1645,14 +1650,17 @@ extern "C" int rssm_backward(rcu_rssm_t h, int T, int B, const float *state0,
   if (!h) return fail(RCU_ERR_INVALID, "rssm_backward: NULL handle");
   h->launches = 0;
   if (!h->set) return fail(RCU_ERR_STATE, "rssm_backward: weights not set");
-  if (T < 1 || B < 1 || !eps || (h->A > 0 && !actions))
+  if (with_actor && h->Hx < 1) return fail(RCU_ERR_STATE, "rssm_backward_actor: actor not set");
+  if (T < 1 || B < 1 || !eps || (!with_actor && h->A > 0 && !actions))
     return fail(RCU_ERR_INVALID, "rssm_backward: need T, B >= 1, eps and actions (action_dim > 0)");
   if ((size_t)T * B > (size_t)INT32_MAX / 8)
     return fail(RCU_ERR_UNSUPPORTED, "rssm_backward: T*B too large");
   cudaStream_t s = (cudaStream_t)stream;
   const int S = h->S, A = h->A, Hd = h->Hd, RH = h->RH, G = 3 * RH, SA = S + A, S2 = 2 * S;
+  const int Hx = with_actor ? h->Hx : 0, SR = S + RH;
   const int M = T * B;
-  const int wmax = std::max(std::max(G, Hd), std::max(SA, S2));
+  const int wmax = std::max(std::max(std::max(G, Hd), std::max(SA, S2)),
+                            with_actor ? std::max(SR, Hx) : 0);
   size_t off = 0;
   auto take = [&](size_t n) { size_t r = off; off += (n + 63) & ~size_t(63); return r; };
   const size_t o_mean = take((size_t)M * S), o_std = take((size_t)M * S),
@@ -1670,6 +1678,13 @@ extern "C" int rssm_backward(rcu_rssm_t h, int T, int B, const float *state0,
                o_w1st = take((size_t)S * Hd), o_w1at = take((size_t)std::max(A, 1) * Hd),
                o_ta = take((size_t)M * wmax), o_tb = take((size_t)M * wmax),
                o_csum = take(colsum_scratch_floats(M, wmax));
+  // actor only: its actions, inputs [s_{t-1}, h_{t-1}], layers and gradients
+  const size_t na = with_actor ? 1 : 0;
+  const size_t o_acts = take(na * M * A), o_xa = take(na * M * SR), o_ua = take(na * M * Hx),
+               o_ha = take(na * M * Hx), o_dact = take(na * M * A), o_dva = take(na * M * A),
+               o_dha = take(na * M * Hx), o_tdha = take(na * B * Hx), o_csa = take(na * B * S),
+               o_ga = take(na * B * RH), o_wa2t = take(na * Hx * A), o_wa1st = take(na * S * Hx),
+               o_wa1ht = take(na * RH * Hx);
   CU(h->bw.ensure(off * 4));
   float *ws = (float *)h->bw.p;
   float *means = ws + o_mean, *stds = ws + o_std, *states = ws + o_st, *bel = ws + o_bel;
@@ -1681,16 +1696,25 @@ extern "C" int rssm_backward(rcu_rssm_t h, int T, int B, const float *state0,
   float *W3T = ws + o_w3t, *W2T = ws + o_w2t, *WhhT = ws + o_whht, *WihT = ws + o_wiht,
         *W1sT = ws + o_w1st, *W1aT = ws + o_w1at, *TA = ws + o_ta, *TB = ws + o_tb,
         *csum = ws + o_csum;
+  float *ACTS = ws + o_acts, *XA = ws + o_xa, *UA = ws + o_ua, *HA = ws + o_ha,
+        *DACT = ws + o_dact, *DVA = ws + o_dva, *DHA = ws + o_dha, *TDHA = ws + o_tdha,
+        *CSA = ws + o_csa, *GA = ws + o_ga, *Wa2T = ws + o_wa2t, *Wa1sT = ws + o_wa1st,
+        *Wa1hT = ws + o_wa1ht;
+  const float *Wa1 = (const float *)h->Wa1.p, *ba1 = (const float *)h->ba1.p;
+  const float *Wa2 = (const float *)h->Wa2.p;
   const float *W1 = (const float *)h->W1.p, *b1 = (const float *)h->b1.p;
   const float *Wih = (const float *)h->Wih.p, *Whh = (const float *)h->Whh.p;
   const float *bih = (const float *)h->bih.p, *bhh = (const float *)h->bhh.p;
   const float *W2 = (const float *)h->W2.p, *b2 = (const float *)h->b2.p;
   const float *W3 = (const float *)h->W3.p, *b3 = (const float *)h->b3.p;
   h->grads_ready = false;
-  // ---- forward again (clears and may set the handle's error word)
-  int rc = rssm_run(h, false, T, B, state0, belief0, actions, eps, means, stds, states, bel,
-                    nullptr, stream);
+  h->actor_grads_ready = false;
+  // ---- forward again (clears and may set the handle's error word); with the
+  // actor it also returns the actions it produced
+  int rc = rssm_run(h, with_actor, T, B, state0, belief0, with_actor ? nullptr : actions, eps,
+                    means, stds, states, bel, with_actor ? ACTS : nullptr, stream);
   if (rc != RCU_OK) return rc;
+  const float *acts = with_actor ? ACTS : actions;
   int launches = h->launches;
   int *err = (int *)h->ctl.p;
   cudaError_t e = cudaSuccess;
@@ -1706,16 +1730,28 @@ extern "C" int rssm_backward(rcu_rssm_t h, int T, int B, const float *state0,
   };
   // ---- everything off the reverse-time chain, over all T*B rows
   h->begin("rssm_bwd_recompute", s);
-  if (e == cudaSuccess) e = launch_rssm_inputs(T, B, S, A, state0, states, actions, IN, s);
+  if (belief0) CU(cudaMemcpyAsync(HP, belief0, (size_t)B * RH * 4, cudaMemcpyDeviceToDevice, s));
+  else CU(cudaMemsetAsync(HP, 0, (size_t)B * RH * 4, s));      // h_{t-1}
+  if (T > 1)
+    CU(cudaMemcpyAsync(HP + (size_t)B * RH, bel, (size_t)(T - 1) * B * RH * 4,
+                       cudaMemcpyDeviceToDevice, s));
+  if (e == cudaSuccess) e = launch_rssm_inputs(T, B, S, A, state0, states, acts, IN, s);
   ++launches;
   gemm(IN, SA, W1, SA, b1, U, Hd, M, Hd, SA);                    // u = W1 [s, a] + b1
   if (e == cudaSuccess) e = launch_elu(U, X, (size_t)M * Hd, s);  // x = ELU(u)
   ++launches;
-  if (belief0) CU(cudaMemcpyAsync(HP, belief0, (size_t)B * RH * 4, cudaMemcpyDeviceToDevice, s));
-  else CU(cudaMemsetAsync(HP, 0, (size_t)B * RH * 4, s));
-  if (T > 1)
-    CU(cudaMemcpyAsync(HP + (size_t)B * RH, bel, (size_t)(T - 1) * B * RH * 4,
-                       cudaMemcpyDeviceToDevice, s));
+  if (with_actor) {
+    // actor input [s_{t-1}, h_{t-1}] (the inputs kernel with h_{t-1} in the
+    // action slot), ua = Wa1 [s, h] + ba1, ha = ELU(ua)
+    if (e == cudaSuccess) e = launch_rssm_inputs(T, B, S, RH, state0, states, HP, XA, s);
+    ++launches;
+    gemm(XA, SR, Wa1, SR, ba1, UA, Hx, M, Hx, SR);
+    if (e == cudaSuccess) e = launch_elu(UA, HA, (size_t)M * Hx, s);
+    ++launches;
+    tr(Wa2, A, Hx, Hx, Wa2T, A);            // [Hx][A]
+    tr(Wa1, Hx, S, SR, Wa1sT, Hx);          // state columns, [S][Hx]
+    tr(Wa1 + S, Hx, RH, SR, Wa1hT, Hx);     // belief columns, [RH][Hx]
+  }
   gemm(X, Hd, Wih, Hd, bih, ZI, G, M, G, Hd);                    // input-side gate pre-activations
   gemm(HP, RH, Whh, RH, bhh, ZH, G, M, G, RH);                   // hidden-side
   if (e == cudaSuccess) e = launch_bwd_prep(T, B, RH, RCU_GRU, ZI, ZH, nullptr, nullptr, nullptr, s);
@@ -1754,6 +1790,22 @@ extern "C" int rssm_backward(rcu_rssm_t h, int T, int B, const float *state0,
     if (e == cudaSuccess) e = launch_elu_grad(TX, U + r0 * Hd, DU + r0 * Hd, (size_t)B * Hd, s);
     ++launches;
     gemm(DU + r0 * Hd, Hd, W1sT, Hd, nullptr, CS, S, B, S, Hd);       // ds_{t-1} part
+    if (with_actor) {
+      // the gradient reaching a_t, back through tanh, Wa2, ELU and Wa1
+      gemm(DU + r0 * Hd, Hd, W1aT, Hd, nullptr, DACT + r0 * A, A, B, A, Hd);
+      if (e == cudaSuccess)
+        e = launch_tanh_grad(DACT + r0 * A, ACTS + r0 * A, DVA + r0 * A, (size_t)B * A, s);
+      ++launches;
+      gemm(DVA + r0 * A, A, Wa2T, A, nullptr, TDHA, Hx, B, Hx, A);
+      if (e == cudaSuccess) e = launch_elu_grad(TDHA, UA + r0 * Hx, DHA + r0 * Hx, (size_t)B * Hx, s);
+      ++launches;
+      gemm(DHA + r0 * Hx, Hx, Wa1sT, Hx, nullptr, CSA, S, B, S, Hx);  // into ds_{t-1}
+      if (e == cudaSuccess) e = launch_add(CS, CSA, (size_t)B * S, s);
+      ++launches;
+      gemm(DHA + r0 * Hx, Hx, Wa1hT, Hx, nullptr, GA, RH, B, RH, Hx); // into dh_{t-1}
+      if (e == cudaSuccess) e = launch_add(GH, GA, (size_t)B * RH, s);
+      ++launches;
+    }
   }
   h->end(s);
   if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rssm_backward: recurrence: %s", cudaGetErrorString(e));
@@ -1764,7 +1816,10 @@ extern "C" int rssm_backward(rcu_rssm_t h, int T, int B, const float *state0,
     e = launch_add(dbelief0, DHZ, (size_t)B * RH, s);
     ++launches;
   }
-  if (A > 0 && dactions) gemm(DU, Hd, W1aT, Hd, nullptr, dactions, A, M, A, Hd);
+  if (with_actor && dactions)
+    CU(cudaMemcpyAsync(dactions, DACT, (size_t)M * A * 4, cudaMemcpyDeviceToDevice, s));
+  else if (A > 0 && dactions)
+    gemm(DU, Hd, W1aT, Hd, nullptr, dactions, A, M, A, Hd);
   // ---- weight gradients: dW = dZ^T Y through K-contiguous transposes, db = column sums
   const size_t nW[10] = {(size_t)Hd * SA, (size_t)Hd, (size_t)G * Hd, (size_t)G * RH, (size_t)G,
                          (size_t)G, (size_t)Hd * RH, (size_t)Hd, (size_t)S2 * Hd, (size_t)S2};
@@ -1785,10 +1840,60 @@ extern "C" int rssm_backward(rcu_rssm_t h, int T, int B, const float *state0,
     if (e == cudaSuccess) e = launch_colsum(w.dz, M, w.nz, csum, w.db, s);
     launches += 2;
   }
+  if (with_actor) {
+    // dWa2 = dVa^T ha, dba2; dWa1 = dHa^T [s, h], dba1
+    CU(h->gwa.ensure(((size_t)Hx * SR + Hx + (size_t)A * Hx + A) * 4));
+    float *gWa1 = (float *)h->gwa.p, *gba1 = gWa1 + (size_t)Hx * SR, *gWa2 = gba1 + Hx,
+          *gba2 = gWa2 + (size_t)A * Hx;
+    const WG wa[2] = {{DVA, A, HA, Hx, gWa2, gba2}, {DHA, Hx, XA, SR, gWa1, gba1}};
+    for (const WG &w : wa) {
+      tr(w.dz, M, w.nz, w.nz, TA, M);
+      tr(w.y, M, w.ny, w.ny, TB, M);
+      gemm(TA, M, TB, M, nullptr, w.dW, w.ny, w.nz, w.ny, M);
+      if (e == cudaSuccess) e = launch_colsum(w.dz, M, w.nz, csum, w.db, s);
+      launches += 2;
+    }
+  }
   h->end(s);
   if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rssm_backward: gradients: %s", cudaGetErrorString(e));
   h->grads_ready = true;
+  h->actor_grads_ready = with_actor;
   h->launches = launches;
+  return RCU_OK;
+}
+
+extern "C" int rssm_backward(rcu_rssm_t h, int T, int B, const float *state0,
+                             const float *belief0, const float *actions, const float *eps,
+                             const float *dmeans, const float *dstds, const float *dstates,
+                             const float *dbeliefs, float *dstate0, float *dbelief0,
+                             float *dactions, void *stream) {
+  return rssm_backward_run(h, false, T, B, state0, belief0, actions, eps, dmeans, dstds, dstates,
+                           dbeliefs, dstate0, dbelief0, dactions, stream);
+}
+
+extern "C" int rssm_backward_actor(rcu_rssm_t h, int T, int B, const float *state0,
+                                   const float *belief0, const float *eps, const float *dmeans,
+                                   const float *dstds, const float *dstates,
+                                   const float *dbeliefs, float *dstate0, float *dbelief0,
+                                   float *dactions, void *stream) {
+  return rssm_backward_run(h, true, T, B, state0, belief0, nullptr, eps, dmeans, dstds, dstates,
+                           dbeliefs, dstate0, dbelief0, dactions, stream);
+}
+
+extern "C" int rssm_get_actor_grads(rcu_rssm_t h, float *dWa1, float *dba1, float *dWa2,
+                                    float *dba2, void *stream) {
+  if (!h) return fail(RCU_ERR_INVALID, "rssm_get_actor_grads: NULL handle");
+  if (!h->actor_grads_ready)
+    return fail(RCU_ERR_STATE, "rssm_get_actor_grads: no rssm_backward_actor has run");
+  const int SR = h->S + h->RH, Hx = h->Hx, A = h->A;
+  const size_t n[4] = {(size_t)Hx * SR, (size_t)Hx, (size_t)A * Hx, (size_t)A};
+  float *dst[4] = {dWa1, dba1, dWa2, dba2};
+  const float *src = (const float *)h->gwa.p;
+  for (int i = 0; i < 4; ++i) {
+    if (dst[i])
+      CU(cudaMemcpyAsync(dst[i], src, n[i] * 4, cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
+    src += n[i];
+  }
   return RCU_OK;
 }
 

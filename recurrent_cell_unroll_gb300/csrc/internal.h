@@ -154,6 +154,8 @@ cudaError_t launch_rssm_inputs(int T, int B, int S, int A, const float *state0,
 cudaError_t launch_elu(const float *pre, float *post, size_t n, cudaStream_t s);
 cudaError_t launch_elu_grad(const float *g, const float *pre, float *out, size_t n,
                             cudaStream_t s);
+// out = g * (1 - y^2)  (y = tanh of something; n elements)
+cudaError_t launch_tanh_grad(const float *g, const float *y, float *out, size_t n, cudaStream_t s);
 // step t: dp (rows t*B..) of the sample and head from dmeans/dstds/dstates
 // (NULL = 0), eps, the head output p [T*B][2S] and cs [B][S] (ds from t+1)
 cudaError_t launch_rssm_sample_grad(int t, int B, int S, const float *dmeans, const float *dstds,

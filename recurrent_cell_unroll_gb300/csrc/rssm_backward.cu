@@ -67,6 +67,16 @@ __global__ void elu_grad_kernel(const float *__restrict__ g, const float *__rest
   }
 }
 
+// out = g * (1 - y^2), the gradient through y = tanh(v)
+__global__ void tanh_grad_kernel(const float *__restrict__ g, const float *__restrict__ y,
+                                 float *__restrict__ out, size_t n) {
+  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+       e += (size_t)gridDim.x * blockDim.x) {
+    const float v = y[e];
+    out[e] = g[e] * (1.f - v * v);
+  }
+}
+
 // Sample and head at step t: ds = dstates_t + cs (the part from step t+1),
 // dmean = dmeans_t + ds, dstd = dstds_t + ds * eps_t;  dp = [dmean,
 // dstd * softplus'(p_std)] with softplus' = sigmoid.  p: [T*B][2S] head
@@ -135,6 +145,12 @@ cudaError_t launch_elu_grad(const float *g, const float *pre, float *out, size_t
                             cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   elu_grad_kernel<<<ew_blocks(n), EW, 0, s>>>(g, pre, out, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tanh_grad(const float *g, const float *y, float *out, size_t n, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  tanh_grad_kernel<<<ew_blocks(n), EW, 0, s>>>(g, y, out, n);
   return cudaGetLastError();
 }
 

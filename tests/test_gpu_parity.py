@@ -969,6 +969,43 @@ def test_rssm_backward_parity(spec, which):
     m.close()
 
 
+@pytest.mark.parametrize("spec", [
+    wl.RSSM_ACTOR,
+    wl.RSSM_B50.scaled(T=6, B=70, state_dim=13, action_dim=5, hidden=72, rnn_hidden=40,
+                       state0_std=1.0, belief0_std=0.5, actor_hidden=37),
+], ids=lambda s: f"T{s.T}-B{s.B}-S{s.state_dim}-A{s.action_dim}-X{s.actor_hidden}")
+def test_rssm_actor_backward_parity(spec):
+    """rssm_backward_actor + rssm_get_weight_grads + rssm_get_actor_grads
+    against the oracle's backward of the actor variant (per tensor: max|gpu -
+    ref| / max|ref| <= 1e-4), including the gradient reaching each action."""
+    inp = wl.make_rssm_inputs(spec, seed=24)
+    g = torch.Generator().manual_seed(96)
+    T, B, S, RH = spec.T, spec.B, spec.state_dim, spec.rnn_hidden
+    grads = {k: torch.randn((T, B, n), generator=g)
+             for k, n in (("dmeans", S), ("dstds", S), ("dstates", S), ("dbeliefs", RH))}
+    dev = torch.device("cuda")
+    m = binding.RSSM(spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden)
+    m.set_weights(inp["weights"])
+    m.set_actor(inp["actor"])
+    with pytest.raises(RuntimeError, match="no rssm_backward_actor"):
+        binding.rssm_get_actor_grads(m.h, {})
+    d = lambda t: None if t is None else t.to(dev)
+    dstate0, dbelief0, dactions, wg, ag = m.backward_actor(
+        d(inp["eps"]), d(inp["state0"]), d(inp["belief0"]), **{k: d(v) for k, v in grads.items()})
+    torch.cuda.synchronize()
+    assert binding.rssm_get_status(m.h) == 0
+    ref = oracle.rssm_backward(inp["weights"], None, inp["eps"], state0=inp["state0"],
+                               belief0=inp["belief0"], actor=inp["actor"], **grads)
+    pairs = [("dstate0", dstate0), ("dbelief0", dbelief0), ("dactions", dactions)]
+    pairs += [("d" + k, wg[k]) for k in binding.RSSM_WEIGHT_NAMES]
+    pairs += [("d" + k, ag[k]) for k in binding.RSSM_ACTOR_NAMES]
+    for name, got in pairs:
+        e = _rel(got.cpu().numpy().astype(np.float64), ref[name])
+        print(f"{name}: rel {e:.2e}")
+        assert e <= BWD_REL, f"{name}: relative max error {e:.3e}"
+    m.close()
+
+
 def test_rssm_profile_phases():
     """RCU_ATTR_PROFILE on an RSSM handle times the unroll and the three phases
     of rssm_backward, once per call each."""
