@@ -235,10 +235,7 @@ def make_rssm_train_runner(spec, inp, dev):
     dstate0 = torch.empty((B, S), device=dev)
     dbelief0 = torch.empty((B, RH), device=dev)
     dactions = torch.empty((T, B, A), device=dev) if A > 0 else None
-    Hd = spec.hidden
-    shapes = {"W1": (Hd, S + A), "b1": (Hd,), "W_ih": (3 * RH, Hd), "W_hh": (3 * RH, RH),
-              "b_ih": (3 * RH,), "b_hh": (3 * RH,), "W2": (Hd, RH), "b2": (Hd,),
-              "W3": (2 * S, Hd), "b3": (2 * S,)}
+    shapes = binding.rssm_weight_shapes(S, A, spec.hidden, RH)
     grads = {k: torch.empty(shapes[k], device=dev) for k in binding.RSSM_WEIGHT_NAMES}
 
     def step():

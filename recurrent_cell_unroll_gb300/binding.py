@@ -348,6 +348,13 @@ def rssm_get_actor_grads(h, grads: dict, stream=None):
 RSSM_WEIGHT_NAMES = ("W1", "b1", "W_ih", "W_hh", "b_ih", "b_hh", "W2", "b2", "W3", "b3")
 
 
+def rssm_weight_shapes(S: int, A: int, Hd: int, RH: int) -> dict:
+    """Shapes of the prior's weights (rssm_set_weights' layouts) by name."""
+    return {"W1": (Hd, S + A), "b1": (Hd,), "W_ih": (3 * RH, Hd), "W_hh": (3 * RH, RH),
+            "b_ih": (3 * RH,), "b_hh": (3 * RH,), "W2": (Hd, RH), "b2": (Hd,),
+            "W3": (2 * S, Hd), "b3": (2 * S,)}
+
+
 def rssm_get_weight_grads(h, grads: dict, stream=None):
     """Copy the last rssm_backward's weight gradients into the device tensors
     of grads (keys of RSSM_WEIGHT_NAMES; missing or None are skipped)."""
@@ -548,9 +555,7 @@ class RSSM:
         rssm_backward(self.h, T, B, state0, belief0, actions, eps, dmeans, dstds, dstates,
                       dbeliefs, dstate0, dbelief0, dactions, stream)
         S, A, Hd, RH = self.S, self.A, self.Hd, self.RH
-        shapes = {"W1": (Hd, S + A), "b1": (Hd,), "W_ih": (3 * RH, Hd), "W_hh": (3 * RH, RH),
-                  "b_ih": (3 * RH,), "b_hh": (3 * RH,), "W2": (Hd, RH), "b2": (Hd,),
-                  "W3": (2 * S, Hd), "b3": (2 * S,)}
+        shapes = rssm_weight_shapes(S, A, Hd, RH)
         grads = {k: torch.empty(shapes[k], device=dev) for k in RSSM_WEIGHT_NAMES}
         rssm_get_weight_grads(self.h, grads, stream)
         return dstate0, dbelief0, dactions, grads
@@ -568,9 +573,7 @@ class RSSM:
         rssm_backward_actor(self.h, T, B, state0, belief0, eps, dmeans, dstds, dstates, dbeliefs,
                             dstate0, dbelief0, dactions, stream)
         S, A, Hd, RH, Ha = self.S, self.A, self.Hd, self.RH, self.Ha
-        shapes = {"W1": (Hd, S + A), "b1": (Hd,), "W_ih": (3 * RH, Hd), "W_hh": (3 * RH, RH),
-                  "b_ih": (3 * RH,), "b_hh": (3 * RH,), "W2": (Hd, RH), "b2": (Hd,),
-                  "W3": (2 * S, Hd), "b3": (2 * S,)}
+        shapes = rssm_weight_shapes(S, A, Hd, RH)
         grads = {k: torch.empty(shapes[k], device=dev) for k in RSSM_WEIGHT_NAMES}
         rssm_get_weight_grads(self.h, grads, stream)
         ashapes = {"Wa1": (Ha, S + RH), "ba1": (Ha,), "Wa2": (A, Ha), "ba2": (A,)}
