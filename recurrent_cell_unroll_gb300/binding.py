@@ -58,6 +58,51 @@ def lib_path() -> str:
     return _build.LIB
 
 
+def signatures() -> dict:
+    """ctypes (restype, argtypes) of every entry point of include/rcu.h."""
+    P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    return {
+        "rcu_last_error": (ctypes.c_char_p, []),
+        "rcu_version": (ctypes.c_char_p, []),
+        "rnn_create": (I, [ctypes.POINTER(P), I, I, I, I, I, I]),
+        "rnn_set_weights": (I, [P, I, I, P, P, P, P, P, P]),
+        "rnn_forward": (I, [P, I, I, P, P, P, P, P, P, P, P, P]),
+        "rnn_get_pack": (I, [P, P, P, P, P]),
+        "rnn_get_status": (I, [P, P]),
+        "rnn_set_attr": (I, [P, I, I64]),
+        "rnn_set_clip": (I, [P, I, I, ctypes.c_double, ctypes.c_double]),
+        "rnn_last_launch_count": (I, [P]),
+        "rnn_destroy": (I, [P]),
+        "rnn_profile_entry": (I, [P, I, ctypes.POINTER(ctypes.c_char_p),
+                                  ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64)]),
+        "rnn_profile_reset": (I, [P]),
+        "rnn_get_trace": (I, [P, P, I, P]),
+        "rnn_lstm_forward_noalloc": (I, [I, I, I, I] + [P] * 10 + [P]),
+        "rssm_create": (I, [ctypes.POINTER(P), I, I, I, I]),
+        "rssm_set_weights": (I, [P] + [P] * 10 + [P]),
+        "rssm_unroll": (I, [P, I, I] + [P] * 8 + [P]),
+        "rssm_get_status": (I, [P, P]),
+        "rssm_last_launch_count": (I, [P]),
+        "rssm_destroy": (I, [P]),
+        "rssm_set_attr": (I, [P, I, I64]),
+        "rssm_get_trace": (I, [P, P, I, P]),
+        "rssm_set_actor": (I, [P, I, P, P, P, P, P]),
+        "rssm_unroll_actor": (I, [P, I, I] + [P] * 8 + [P]),
+        "rnn_forward_host": (I, [P, I, I] + [P] * 8),
+        "rnn_backward": (I, [P, I, I] + [P] * 11),
+        "rnn_get_weight_grads": (I, [P, I, I, P, P, P, P, P, P]),
+        "rssm_unroll_host": (I, [P, I, I] + [P] * 8 + [P]),
+        "rssm_unroll_actor_host": (I, [P, I, I] + [P] * 8 + [P]),
+        "rssm_backward": (I, [P, I, I] + [P] * 12),
+        "rssm_get_weight_grads": (I, [P] + [P] * 11),
+        "rssm_backward_actor": (I, [P, I, I] + [P] * 11),
+        "rssm_get_actor_grads": (I, [P] * 6),
+        "rssm_profile_entry": (I, [P, I, ctypes.POINTER(ctypes.c_char_p),
+                                   ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64)]),
+        "rssm_profile_reset": (I, [P]),
+    }
+
+
 def load(path: Optional[str] = None):
     """Load librcu.so (raises if it has not been built)."""
     global _lib
@@ -69,47 +114,7 @@ def load(path: Optional[str] = None):
             raise RuntimeError(f"librcu.so not found at {p}: build it with "
                                "recurrent_cell_unroll_gb300._build.build()")
         lib = ctypes.CDLL(p)
-        P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
-        sig = {
-            "rcu_last_error": (ctypes.c_char_p, []),
-            "rcu_version": (ctypes.c_char_p, []),
-            "rnn_create": (I, [ctypes.POINTER(P), I, I, I, I, I, I]),
-            "rnn_set_weights": (I, [P, I, I, P, P, P, P, P, P]),
-            "rnn_forward": (I, [P, I, I, P, P, P, P, P, P, P, P, P]),
-            "rnn_get_pack": (I, [P, P, P, P, P]),
-            "rnn_get_status": (I, [P, P]),
-            "rnn_set_attr": (I, [P, I, I64]),
-            "rnn_set_clip": (I, [P, I, I, ctypes.c_double, ctypes.c_double]),
-            "rnn_last_launch_count": (I, [P]),
-            "rnn_destroy": (I, [P]),
-            "rnn_profile_entry": (I, [P, I, ctypes.POINTER(ctypes.c_char_p),
-                                      ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64)]),
-            "rnn_profile_reset": (I, [P]),
-            "rnn_get_trace": (I, [P, P, I, P]),
-            "rnn_lstm_forward_noalloc": (I, [I, I, I, I] + [P] * 10 + [P]),
-            "rssm_create": (I, [ctypes.POINTER(P), I, I, I, I]),
-            "rssm_set_weights": (I, [P] + [P] * 10 + [P]),
-            "rssm_unroll": (I, [P, I, I] + [P] * 8 + [P]),
-            "rssm_get_status": (I, [P, P]),
-            "rssm_last_launch_count": (I, [P]),
-            "rssm_destroy": (I, [P]),
-            "rssm_set_attr": (I, [P, I, I64]),
-            "rssm_get_trace": (I, [P, P, I, P]),
-            "rssm_set_actor": (I, [P, I, P, P, P, P, P]),
-            "rssm_unroll_actor": (I, [P, I, I] + [P] * 8 + [P]),
-            "rnn_forward_host": (I, [P, I, I] + [P] * 8),
-            "rnn_backward": (I, [P, I, I] + [P] * 11),
-            "rnn_get_weight_grads": (I, [P, I, I, P, P, P, P, P, P]),
-            "rssm_unroll_host": (I, [P, I, I] + [P] * 8 + [P]),
-            "rssm_unroll_actor_host": (I, [P, I, I] + [P] * 8 + [P]),
-            "rssm_backward": (I, [P, I, I] + [P] * 12),
-            "rssm_get_weight_grads": (I, [P] + [P] * 11),
-            "rssm_backward_actor": (I, [P, I, I] + [P] * 11),
-            "rssm_get_actor_grads": (I, [P] * 6),
-            "rssm_profile_entry": (I, [P, I, ctypes.POINTER(ctypes.c_char_p),
-                                       ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64)]),
-            "rssm_profile_reset": (I, [P]),
-        }
+        sig = signatures()
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
             fn.restype = res

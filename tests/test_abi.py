@@ -79,3 +79,55 @@ def test_constants_match_header():
         assert n in defs, f"{n} is not defined in rcu.h"
         assert getattr(binding, n) == defs[n], n
 
+
+
+def _declarations():
+    """{name: (return type, [parameter declarations])} of every RCU_API function."""
+    src = open(os.path.join(ROOT, "include", "rcu.h")).read()
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    out = {}
+    for m in re.finditer(r"RCU_API\s+([\w\s\*]*?)\b(\w+)\s*\(([^)]*)\)\s*;", src):
+        params = [p.strip() for p in m.group(3).split(",")]
+        if params == ["void"] or params == [""]:
+            params = []
+        out[m.group(2)] = (" ".join(m.group(1).split()), params)
+    return out
+
+
+def _kind_of_c(decl: str) -> str:
+    decl = " ".join(decl.split())
+    if "*" in decl or decl.startswith(("rcu_rnn_t", "rcu_rssm_t")):
+        return "ptr"
+    if decl.startswith("int64_t"):
+        return "i64"
+    if decl.startswith("double"):
+        return "f64"
+    if decl.startswith("float"):
+        return "f32"
+    if decl.startswith("int"):
+        return "i32"
+    raise AssertionError(f"unclassified parameter {decl!r}")
+
+
+def _kind_of_ctypes(t) -> str:
+    if t in (ctypes.c_void_p, ctypes.c_char_p) or isinstance(t, type(ctypes.POINTER(ctypes.c_int))):
+        return "ptr"
+    return {ctypes.c_int: "i32", ctypes.c_int64: "i64", ctypes.c_double: "f64",
+            ctypes.c_float: "f32"}[t]
+
+
+def test_binding_signatures_match_the_header():
+    """Every declared entry point has ctypes argtypes (without them a pointer
+    argument would be passed as a C int), with the header's parameter count
+    and kinds, and a matching return type."""
+    decls = _declarations()
+    sigs = binding.signatures()
+    assert set(decls) == set(sigs)
+    for name, (ret, params) in decls.items():
+        res, args = sigs[name]
+        want = [_kind_of_c(p) for p in params]
+        got = [_kind_of_ctypes(a) for a in args]
+        assert got == want, f"{name}: binding {got} vs header {want}"
+        assert (res is ctypes.c_char_p) == ("char" in ret), name
+        if "char" not in ret:
+            assert res is ctypes.c_int and ret == "int", name
