@@ -65,7 +65,7 @@ def _load():
             lib.oracle_rssm_unroll2.argtypes = ([i, i, i, i, i, i] + [P] * 14 + [P, P, P, P, P, i, i]
                                                 + [i, P, P, P, P, P])
             lib.oracle_rnn_backward.restype = i
-            lib.oracle_rnn_backward.argtypes = [i] * 9 + [P] * 16 + [i]
+            lib.oracle_rnn_backward.argtypes = [i] * 9 + [P] * 16 + [i, P]
             lib.oracle_rssm_backward.restype = i
             lib.oracle_rssm_backward.argtypes = [i] * 6 + [P] * 31
             lib.oracle_rssm_backward2.restype = i
@@ -174,10 +174,11 @@ def rnn_forward(cell: int, x, weights, *, hidden: int, proj: int = 0, bidirectio
 
 def rnn_backward(cell: int, x, weights, dy, *, hidden: int, proj: int = 0,
                  bidirectional: bool = False, lengths=None, h0=None, c0=None, dh_n=None,
-                 dc_n=None, bf16_weights: bool = False, threads: int = 0):
+                 dc_n=None, bf16_weights: bool = False, threads: int = 0, cell_clip=None,
+                 proj_clip=None):
     """Backward pass through time of a stacked LSTM / GRU, or LSTM with
     projection, optionally bidirectional, over padded or variable-length
-    batches (no clipping), in fp64:
+    batches, in fp64:
     the gradients of a loss with dL/dy = dy [T,B,D*Ho] (and dL/dh_n
     [L*D,B,Ho], dL/dc_n [L*D,B,H], None = 0; Ho = proj or hidden).
 
@@ -188,7 +189,9 @@ def rnn_backward(cell: int, x, weights, dy, *, hidden: int, proj: int = 0,
     weights' shapes.  lengths: None or int32 [B] in [1, T]; row b runs its
     first len_b steps as in rnn_forward and its dx is 0 beyond them.
     bf16_weights: the weight matrices are rounded to bf16 first (biases stay
-    fp32), as in rnn_forward.
+    fp32), as in rnn_forward.  cell_clip / proj_clip: None or (lo, hi), the
+    LSTM clipping of rnn_forward; a clamp passes the gradient where its input
+    lies in [lo, hi].
     """
     lib = _load()
     x = _f32(x)
@@ -209,6 +212,12 @@ def rnn_backward(cell: int, x, weights, dy, *, hidden: int, proj: int = 0,
         arr[i] = _LayerW(*[_ptr(v) for v in vals])
     h0a, c0a, dya, dhn, dcn = _f32(h0), _f32(c0), _f32(dy), _f32(dh_n), _f32(dc_n)
     ln = _i32(lengths)  # kept alive across the call
+    clip = None
+    if cell_clip is not None or proj_clip is not None:
+        inf = float("inf")
+        cl = cell_clip if cell_clip is not None else (-inf, inf)
+        pl = proj_clip if proj_clip is not None else (-inf, inf)
+        clip = np.array([cl[0], cl[1], pl[0], pl[1]], np.float64)
     in_l = [in_dim if i // D == 0 else D * Ho for i in range(LD)]
     dx = np.zeros((T, B, in_dim))
     dh0 = np.zeros((LD, B, Ho))
@@ -223,7 +232,7 @@ def rnn_backward(cell: int, x, weights, dy, *, hidden: int, proj: int = 0,
                                  _ptr(x), _ptr(ln), _ptr(h0a), _ptr(c0a), ctypes.addressof(arr), _ptr(dya),
                                  _ptr(dhn), _ptr(dcn), _ptr(dx), _ptr(dh0), _ptr(dc0),
                                  _ptr(dwih), _ptr(dwhh), _ptr(dbih), _ptr(dbhh),
-                                 _ptr(dwhr) if proj > 0 else None, int(threads))
+                                 _ptr(dwhr) if proj > 0 else None, int(threads), _ptr(clip))
     if rc != 0:
         raise ValueError("oracle_rnn_backward: invalid arguments")
     offs = np.cumsum([0] + [nG * H * k for k in in_l])

@@ -483,8 +483,8 @@ int oracle_num_threads_default(void) {
 
 /* ---------------------------------------------------------------------- */
 /* Backward pass through time (BPTT) of the stacked unidirectional          */
-/* LSTM / GRU, optionally LSTM with projection, without lengths or          */
-/* clipping: the training use of the unrolled cell behind the RSSM page's   */
+/* LSTM / GRU, optionally LSTM with projection: the training use of the    */
+/* unrolled cell behind the RSSM page's                                     */
 /* Motivation and the LSTMP page's training discussion.  The gradient of a  */
 /* scalar loss whose derivative with respect to y is dy [T,B,Ho] (and to    */
 /* h_n / c_n is dh_n [L,B,Ho] / dc_n [L,B,H], NULL = 0; Ho = proj or H) is  */
@@ -516,14 +516,19 @@ int oracle_num_threads_default(void) {
 /* dh_n enters at its last processed step and dx is 0 at t >= len_b.        */
 /* bf16_weights: the weight matrices are first rounded                     */
 /* to bf16 (the forward oracle's convention; biases stay fp32).             */
+/* clip: NULL or {cell_lo, cell_hi, proj_lo, proj_hi} as in the forward     */
+/* (LSTM only): a clamp passes the gradient where the unclamped value lies  */
+/* in [lo, hi] (bounds included) and stops it elsewhere, so dc and dh are   */
+/* masked by that condition right after they reach the clamped value.       */
 int oracle_rnn_backward(int cell, int bidir, int layers, int in_dim, int hidden, int proj,
                         int bf16_weights, int T, int B, const float *x, const int32_t *lengths,
                         const float *h0, const float *c0,
                         const oracle_layer_w *w, const float *dy, const float *dh_n,
                         const float *dc_n, double *dx, double *dh0, double *dc0, double *dW_ih,
                         double *dW_hh, double *db_ih, double *db_hh, double *dW_hr,
-                        int nthreads) {
+                        int nthreads, const double *clip) {
     if (cell != OR_LSTM && cell != OR_GRU) return -1;
+    if (clip && cell != OR_LSTM) return -1;
     if (layers < 1 || in_dim < 1 || hidden < 1 || T < 1 || B < 1 || !x || !dy) return -1;
     if (proj < 0 || (proj > 0 && cell != OR_LSTM)) return -1;
     if (lengths)
@@ -581,6 +586,9 @@ int oracle_rnn_backward(int cell, int bidir, int layers, int in_dim, int hidden,
         double *cs = (double *)malloc((size_t)LD * (T + 1) * H * sizeof(double));
         double *ms = (double *)malloc((size_t)LD * T * H * sizeof(double));
         double *gt = (double *)malloc((size_t)LD * T * (G + H) * sizeof(double));
+        /* clipping: the unclamped cell state and projection of every step */
+        double *craw = (double *)malloc((size_t)LD * T * H * sizeof(double));
+        double *hraw = (double *)malloc((size_t)LD * T * (P > 0 ? P : 1) * sizeof(double));
         double *dX = (double *)malloc((size_t)T * wmax * sizeof(double));
         double *dY = (double *)malloc((size_t)T * DHo * sizeof(double));
         double *dh = (double *)malloc((size_t)Ho * sizeof(double));
@@ -608,6 +616,8 @@ int oracle_rnn_backward(int cell, int bidir, int layers, int in_dim, int hidden,
                     double *hl = hs + (size_t)i * (T + 1) * Ho, *cl = cs + (size_t)i * (T + 1) * H;
                     double *ml = ms + (size_t)i * T * H;
                     double *gl = gt + (size_t)i * T * (G + H);
+                    double *crl = craw + (size_t)i * T * H;
+                    double *hrl = hraw + (size_t)i * T * (P > 0 ? P : 1);
                     for (int k = 0; k < Ho; ++k) hl[k] = h0 ? (double)h0[((size_t)i * B + b) * Ho + k] : 0.0;
                     for (int k = 0; k < H; ++k)
                         cl[k] = (lstm && c0) ? (double)c0[((size_t)i * B + b) * H + k] : 0.0;
@@ -631,6 +641,8 @@ int oracle_rnn_backward(int cell, int bidir, int layers, int in_dim, int hidden,
                                 const double gg = tanh(pre[2 * H + u] + pre[G + 2 * H + u]);
                                 const double o = sigmoid(pre[3 * H + u] + pre[G + 3 * H + u]);
                                 cn_[u] = f * cl[(size_t)s2 * H + u] + ig * gg;
+                                crl[(size_t)s2 * H + u] = cn_[u];
+                                if (clip) cn_[u] = clampd(cn_[u], clip[0], clip[1]);
                                 mt[u] = o * tanh(cn_[u]);
                                 g[u] = ig; g[H + u] = f; g[2 * H + u] = gg; g[3 * H + u] = o;
                             } else {
@@ -647,7 +659,8 @@ int oracle_rnn_backward(int cell, int bidir, int layers, int in_dim, int hidden,
                             for (int q = 0; q < P; ++q) {
                                 double a2 = 0.0;
                                 for (int k = 0; k < H; ++k) a2 += Whr[i][(size_t)q * H + k] * mt[k];
-                                hn_[q] = a2;
+                                hrl[(size_t)s2 * P + q] = a2;
+                                hn_[q] = clip ? clampd(a2, clip[2], clip[3]) : a2;
                             }
                         } else {
                             memcpy(hn_, mt, (size_t)H * sizeof(double));
@@ -670,6 +683,8 @@ int oracle_rnn_backward(int cell, int bidir, int layers, int in_dim, int hidden,
                     const double *hl = hs + (size_t)i * (T + 1) * Ho, *cl = cs + (size_t)i * (T + 1) * H;
                     const double *ml = ms + (size_t)i * T * H;
                     const double *gl = gt + (size_t)i * T * (G + H);
+                    const double *crl = craw + (size_t)i * T * H;
+                    const double *hrl = hraw + (size_t)i * T * (P > 0 ? P : 1);
                     for (int k = 0; k < Ho; ++k) dhp[k] = dh_n ? (double)dh_n[((size_t)i * B + b) * Ho + k] : 0.0;
                     for (int k = 0; k < H; ++k)
                         dc[k] = (lstm && dc_n) ? (double)dc_n[((size_t)i * B + b) * H + k] : 0.0;
@@ -679,6 +694,11 @@ int oracle_rnn_backward(int cell, int bidir, int layers, int in_dim, int hidden,
                         const double *hp = hl + (size_t)s2 * Ho, *xt = Xl + (size_t)t * wmax;
                         const double *mt = ml + (size_t)s2 * H;
                         for (int q = 0; q < Ho; ++q) dh[q] = dY[(size_t)t * DHo + (size_t)d * Ho + q] + dhp[q];
+                        if (P > 0 && clip)  /* through the projection clamp */
+                            for (int q = 0; q < P; ++q) {
+                                const double v = hrl[(size_t)s2 * P + q];
+                                if (v < clip[2] || v > clip[3]) dh[q] = 0.0;
+                            }
                         if (P > 0) {
                             double *gWr = gWhr + (size_t)i * P * H;
                             for (int k = 0; k < H; ++k) {
@@ -696,7 +716,11 @@ int oracle_rnn_backward(int cell, int bidir, int layers, int in_dim, int hidden,
                                 const double ig = g[u], f = g[H + u], gg = g[2 * H + u], o = g[3 * H + u];
                                 const double c = cl[(size_t)(s2 + 1) * H + u], cp = cl[(size_t)s2 * H + u];
                                 const double tc = tanh(c);
-                                const double dcu = dc[u] + dm[u] * o * (1.0 - tc * tc);
+                                double dcu = dc[u] + dm[u] * o * (1.0 - tc * tc);
+                                if (clip) {  /* through the cell-state clamp */
+                                    const double v = crl[(size_t)s2 * H + u];
+                                    if (v < clip[0] || v > clip[1]) dcu = 0.0;
+                                }
                                 dA[u] = dcu * gg * ig * (1.0 - ig);
                                 dA[H + u] = dcu * cp * f * (1.0 - f);
                                 dA[2 * H + u] = dcu * ig * (1.0 - gg * gg);
@@ -751,7 +775,7 @@ int oracle_rnn_backward(int cell, int bidir, int layers, int in_dim, int hidden,
                 }
             }
         }
-        free(X); free(hs); free(cs); free(ms); free(gt); free(dX); free(dY);
+        free(X); free(hs); free(cs); free(ms); free(gt); free(craw); free(hraw); free(dX); free(dY);
         free(dh); free(dm); free(dc); free(dhp); free(dA); free(dR); free(pre);
     }
     /* sum the per-thread accumulators in thread order */

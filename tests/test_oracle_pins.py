@@ -1230,3 +1230,104 @@ def test_rssm_constant_actor_backward_reduces_to_given_actions():
     assert np.all(got["dWa1"] == 0.0) and np.all(got["dba1"] == 0.0)
     np.testing.assert_allclose(got["dba2"], (1 - acts ** 2) * got["dactions"].sum((0, 1)),
                                rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------------------------------- backward with clipping
+
+def _clipped_lstm_loss(x, ws, H, P, h0, c0, dy, dhn, dcn, cclip, pclip):
+    """A stacked unidirectional LSTM (optionally with projection) written out
+    with torch.clamp on the cell state and the projection, float64; returns the
+    loss <y, dy> + <h_n, dhn> + <c_n, dcn>."""
+    L = len(ws)
+    Ho = P if P else H
+    layer_in = x
+    loss = torch.zeros((), dtype=torch.float64)
+    for l in range(L):
+        w = ws[l]
+        h, c = h0[l], c0[l]
+        ys = []
+        for t in range(layer_in.shape[0]):
+            z = layer_in[t] @ w["w_ih"].T + w["b_ih"] + h @ w["w_hh"].T + w["b_hh"]
+            i, f, g, o = z.split(H, dim=-1)
+            c = torch.sigmoid(f) * c + torch.sigmoid(i) * torch.tanh(g)
+            if cclip is not None:
+                c = torch.clamp(c, cclip[0], cclip[1])
+            m = torch.sigmoid(o) * torch.tanh(c)
+            h = m @ w["w_hr"].T if P else m
+            if P and pclip is not None:
+                h = torch.clamp(h, pclip[0], pclip[1])
+            ys.append(h)
+        layer_in = torch.stack(ys)
+        loss = loss + (h * dhn[l]).sum() + (c * dcn[l]).sum()
+    return loss + (layer_in * dy).sum()
+
+
+@pytest.mark.parametrize("proj", [0, 4])
+def test_bptt_clipping_against_torch_autograd(proj):
+    """Cell-state (and projection) clipping: the oracle's gradients equal
+    torch float64 autograd through the clamps, with bounds that clamp a good
+    share of the values."""
+    rng = np.random.default_rng(81 + proj)
+    T, B, in_dim, H, layers = 6, 3, 4, 5, 2
+    ws = _rand_weights(rng, oracle.LSTM, layers, in_dim, H, proj=proj, scale=1.5)
+    Ho = proj if proj else H
+    x = rng.standard_normal((T, B, in_dim)).astype(np.float32)
+    h0 = (0.5 * rng.standard_normal((layers, B, Ho))).astype(np.float32)
+    c0 = (0.5 * rng.standard_normal((layers, B, H))).astype(np.float32)
+    dy = rng.standard_normal((T, B, Ho)).astype(np.float32)
+    dhn = rng.standard_normal((layers, B, Ho)).astype(np.float32)
+    dcn = rng.standard_normal((layers, B, H)).astype(np.float32)
+    cclip, pclip = (-0.3, 0.4), ((-0.2, 0.25) if proj else None)
+    g = oracle.rnn_backward(oracle.LSTM, x, ws, dy, hidden=H, proj=proj, h0=h0, c0=c0,
+                            dh_n=dhn, dc_n=dcn, cell_clip=cclip, proj_clip=pclip)
+    d = lambda a: torch.from_numpy(np.asarray(a)).double()
+    tw = [{k: (d(v).requires_grad_() if v is not None else None) for k, v in w.items()}
+          for w in ws]
+    xt, h0t, c0t = d(x).requires_grad_(), d(h0).requires_grad_(), d(c0).requires_grad_()
+    loss = _clipped_lstm_loss(xt, tw, H, proj, h0t, c0t, d(dy), d(dhn), d(dcn), cclip, pclip)
+    loss.backward()
+    # the bounds do clamp (else this would test nothing)
+    y, _, cn = oracle.rnn_forward(oracle.LSTM, x, ws, hidden=H, proj=proj, h0=h0, c0=c0)
+    assert (np.abs(cn) > 0.4).any() and (y.max() > 0.25 if proj else True)
+    tol = dict(rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(g["dx"], xt.grad.numpy(), **tol)
+    np.testing.assert_allclose(g["dh0"], h0t.grad.numpy(), **tol)
+    np.testing.assert_allclose(g["dc0"], c0t.grad.numpy(), **tol)
+    for l in range(layers):
+        for k in ("w_ih", "w_hh", "b_ih", "b_hh") + (("w_hr",) if proj else ()):
+            np.testing.assert_allclose(g["d" + k][l], tw[l][k].grad.numpy(), **tol,
+                                       err_msg=f"d{k}[{l}]")
+
+
+def test_bptt_cell_clip_to_zero_stops_every_gradient():
+    """Clamping the cell state to [0, 0] makes every c_t and h_t zero whatever
+    the inputs (a closed form): no output depends on any input, weight or
+    initial state, so dx, dh0, dc0 and all weight gradients are exactly 0."""
+    rng = np.random.default_rng(85)
+    T, B, in_dim, H = 5, 2, 3, 4
+    ws = _rand_weights(rng, oracle.LSTM, 1, in_dim, H)
+    x = rng.standard_normal((T, B, in_dim)).astype(np.float32)
+    dy = rng.standard_normal((T, B, H)).astype(np.float32)
+    dcn = rng.standard_normal((1, B, H)).astype(np.float32)
+    g = oracle.rnn_backward(oracle.LSTM, x, ws, dy, hidden=H, dc_n=dcn, cell_clip=(0.0, 0.0))
+    for k in ("dx", "dh0", "dc0"):
+        assert np.all(g[k] == 0.0), k
+    for k in ("dw_ih", "dw_hh", "db_ih", "db_hh"):
+        assert np.all(g[k][0] == 0.0), k
+
+
+def test_bptt_infinite_clip_bounds_change_nothing():
+    rng = np.random.default_rng(86)
+    T, B, in_dim, H, P = 5, 2, 3, 6, 4
+    ws = _rand_weights(rng, oracle.LSTM, 2, in_dim, H, proj=P)
+    x = rng.standard_normal((T, B, in_dim)).astype(np.float32)
+    dy = rng.standard_normal((T, B, P)).astype(np.float32)
+    inf = float("inf")
+    a = oracle.rnn_backward(oracle.LSTM, x, ws, dy, hidden=H, proj=P)
+    b = oracle.rnn_backward(oracle.LSTM, x, ws, dy, hidden=H, proj=P, cell_clip=(-inf, inf),
+                            proj_clip=(-inf, inf))
+    for k in ("dx", "dh0", "dc0"):
+        assert np.array_equal(a[k], b[k]), k
+    for k in ("dw_ih", "dw_hh", "db_ih", "db_hh", "dw_hr"):
+        for l in range(2):
+            assert np.array_equal(a[k][l], b[k][l]), k
