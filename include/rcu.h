@@ -201,9 +201,11 @@ RCU_API int rnn_forward_host(rcu_rnn_t h, int T, int B, const float *x, const in
  * Backward pass through time (BPTT), the training use of the unrolled cell
  * ("[Feature Request] CUDNN version of RSSM", pytorch/rl issue 366,
  * Motivation; "Integrating CuDNN API for LSTMs with projections",
- * pytorch/pytorch issue 46213, training discussion).  Handles without
- * clipping (else RCU_ERR_UNSUPPORTED): LSTM, GRU and LSTM with projection,
- * uni- or bidirectional, over padded or variable-length batches; on an
+ * pytorch/pytorch issue 46213, training discussion).  LSTM, GRU and LSTM
+ * with projection, uni- or bidirectional, over padded or variable-length
+ * batches, with or without cell-state clipping (the clamp passes the
+ * gradient where the unclamped cell value lies within the bounds; a
+ * projection clip gives RCU_ERR_UNSUPPORTED); on an
  * RCU_BF16 handle, the fp32 gradient of the model with the bf16-rounded
  * weights its forward uses.  Given the forward's inputs x [T,B,in], lengths
  * (device int32 [B], each in [1, T], or NULL = all T; as rnn_forward),

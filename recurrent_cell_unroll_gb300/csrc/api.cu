@@ -1065,8 +1065,8 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
   h->launches = 0;
   for (auto &w : h->lw)
     if (!w.set) return fail(RCU_ERR_STATE, "rnn_backward: weights missing for some layer/direction");
-  if (h->cclip || h->pclip)
-    return fail(RCU_ERR_UNSUPPORTED, "rnn_backward: networks without clipping");
+  if (h->pclip)
+    return fail(RCU_ERR_UNSUPPORTED, "rnn_backward: projection clipping (cell clipping is supported)");
   if (T < 1 || B < 1 || !x || !dy) return fail(RCU_ERR_INVALID, "rnn_backward: need T, B >= 1, x and dy");
   if (h->cell == RCU_GRU && (c0 || dc_n || dc0))
     return fail(RCU_ERR_INVALID, "rnn_backward: c0/dc_n/dc0 are LSTM-only");
@@ -1104,6 +1104,8 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
                o_tmp = take(D > 1 ? TBK : 0),
                // variable lengths: dy of one direction, zero past each row's end
                o_dym = take(lengths ? TBO : 0),
+               // cell clipping: the unclamped cell state of every step
+               o_cr = take(cell == RCU_LSTM && h->cclip ? TBH : 0),
                o_xm = take(lengths ? (size_t)M * h->in_l[0] : 0), o_ctl = take(64);
   CU(h->bw.ensure(off * 4));
   float *wsf = (float *)h->bw.p;
@@ -1118,6 +1120,7 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
         *T6 = wsf + o_t6;
   float *XR = wsf + o_xr, *YD = wsf + o_yd, *DYD = wsf + o_dyd, *DXR = wsf + o_dxr,
         *TMP = wsf + o_tmp, *DYM = wsf + o_dym, *XM = wsf + o_xm;
+  float *CR = (cell == RCU_LSTM && h->cclip) ? wsf + o_cr : nullptr;
   unsigned *ctr = (unsigned *)(wsf + o_ctl);
   if ((int)h->gw.size() < L * D) h->gw.resize((size_t)L * D);
   h->grads_ready = false;
@@ -1176,7 +1179,8 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     h->end(s);
     const float *c0l = c0 ? c0 + (size_t)i * B * H : nullptr;
     h->begin("bwd_prep", s);
-    if (e == cudaSuccess) e = launch_bwd_prep(T, B, H, cell, zin, zh, c0l, cs, ms, s);
+    if (e == cudaSuccess)
+      e = launch_bwd_prep(T, B, H, cell, zin, zh, c0l, cs, ms, s, CR, h->cclip_lo, h->cclip_hi);
     h->end(s);
     if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: recompute: %s", cudaGetErrorString(e));
     // projection: dy' = dy (+ dh_n at the last step), A = dy' W_hr, F = W_hh W_hr
@@ -1207,6 +1211,7 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     a.dhn = P > 0 ? nullptr : dhnl;
     a.dcn = dc_n ? dc_n + (size_t)i * B * H : nullptr;
     a.lengths = lengths;
+    a.cr = CR; a.clo = h->cclip_lo; a.chi = h->cclip_hi;
     a.DA = DA; a.DR = DR;
     a.dh0 = (P > 0 || !dh0) ? nullptr : dh0 + (size_t)i * B * H;
     a.dc0 = dc0 ? dc0 + (size_t)i * B * H : nullptr;

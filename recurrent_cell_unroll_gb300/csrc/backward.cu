@@ -32,9 +32,12 @@ constexpr int NT = 512;
 // entry and the activated gates on exit (LSTM i, f, g, o; GRU r, z, n);
 // zh = H_prev W_hh^T + b_hh is only read.  cs[t][b][u] = c_t (LSTM);
 // ms[t][b][u] = m_t = o tanh(c_t) when ms is given (LSTM with projection).
+// Cell clipping (cr given): cr[t][b][u] = f c' + i g before the clamp, and
+// c_t = clamp(that, clo, chi) as in the forward.
 __global__ void bwd_prep_kernel(int T, int B, int H, int cell, float *__restrict__ zin,
                                 const float *__restrict__ zh, const float *__restrict__ c0,
-                                float *__restrict__ cs, float *__restrict__ ms) {
+                                float *__restrict__ cs, float *__restrict__ ms,
+                                float *__restrict__ cr, float clo, float chi) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= B * H) return;
   const int b = e / H, u = e % H;
@@ -50,6 +53,10 @@ __global__ void bwd_prep_kernel(int T, int B, int H, int cell, float *__restrict
       const float g = tanh_f(a[2 * H + u] + h[2 * H + u]);
       const float o = sigmoid_f(a[3 * H + u] + h[3 * H + u]);
       c = f * c + i * g;
+      if (cr) {
+        cr[r * H + u] = c;
+        c = fminf(fmaxf(c, clo), chi);
+      }
       cs[r * H + u] = c;
       if (ms) ms[r * H + u] = o * tanh_f(c);
       a[u] = i; a[H + u] = f; a[2 * H + u] = g; a[3 * H + u] = o;
@@ -93,6 +100,8 @@ struct BwdParams {
   const float *dy;    // [T*B][H]
   const float *dhn, *dcn;  // [B][H] or NULL
   const int32_t *lengths;  // [B] or NULL: row b runs steps 0 .. len_b - 1 only
+  const float *cr;    // LSTM cell clipping: [T*B][H] unclamped c_t, or NULL
+  float clo, chi;     // its bounds: the clamp passes dc where clo <= cr <= chi
   float *DA, *DR;     // [T*B][G]: input-side and hidden-side gate gradients (LSTM: DR == DA)
   float *dh0, *dc0;   // [B][H] or NULL
   unsigned *ctr;
@@ -159,7 +168,11 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
         const float c = p.cs[r * H + u];
         const float cp = t > 0 ? p.cs[(r - B) * H + u] : (p.c0 ? p.c0[(size_t)b * H + u] : 0.f);
         const float tc = tanh_f(c);
-        const float dc = dcs[e] + dh * o * (1.f - tc * tc);
+        float dc = dcs[e] + dh * o * (1.f - tc * tc);
+        if (p.cr) {  // through the cell-state clamp
+          const float v = p.cr[r * H + u];
+          if (v < p.clo || v > p.chi) dc = 0.f;
+        }
         da[u] = dc * gg * i * (1.f - i);
         da[H + u] = dc * cp * f * (1.f - f);
         da[2 * H + u] = dc * i * (1.f - gg * gg);
@@ -358,9 +371,11 @@ RecPlan plan_rec(int H, int B, int nG, int nsm) {
 }  // namespace
 
 cudaError_t launch_bwd_prep(int T, int B, int H, int cell, float *zin, const float *zh,
-                            const float *c0, float *cs, float *ms, cudaStream_t s) {
+                            const float *c0, float *cs, float *ms, cudaStream_t s, float *cr,
+                            float clo, float chi) {
   const int n = B * H;
-  bwd_prep_kernel<<<ceil_div(n, 256), 256, 0, s>>>(T, B, H, cell, zin, zh, c0, cs, ms);
+  bwd_prep_kernel<<<ceil_div(n, 256), 256, 0, s>>>(T, B, H, cell, zin, zh, c0, cs, ms, cr, clo,
+                                                   chi);
   return cudaGetLastError();
 }
 
@@ -450,6 +465,7 @@ cudaError_t launch_bwd_rec(const BwdRecArgs &a, int nsm, cudaStream_t s) {
   p.Whh = a.Whh; p.ldw = a.ldw;
   p.gates = a.gates; p.zh = a.zh; p.cs = a.cs; p.c0 = a.c0; p.hp = a.hp;
   p.dy = a.dy; p.dhn = a.dhn; p.dcn = a.dcn; p.lengths = a.lengths;
+  p.cr = a.cr; p.clo = a.clo; p.chi = a.chi;
   p.DA = a.DA; p.DR = a.DR; p.dh0 = a.dh0; p.dc0 = a.dc0;
   p.ctr = a.ctr; p.err = a.err; p.timeout_ns = a.timeout_ns; p.drop_arrival = a.drop_arrival;
   const size_t smem = rp.smem;

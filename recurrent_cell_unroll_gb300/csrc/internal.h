@@ -129,9 +129,11 @@ bool rssm_supported(int S, int A, int Hd, int RH, int Hx = 0);
 // ---- backward.cu: backward pass through time (fp32, unidirectional) ---------
 // zin: X W_ih^T + b_ih in, activated gates out; zh: H_prev W_hh^T + b_hh;
 // cs: LSTM cell sequence out; ms: m_t = o tanh(c_t) out (projection) or NULL.
-// Parallel over B*H, sequential over T.
+// cr: LSTM cell clipping, the unclamped c_t out (c_t itself clamped to
+// [clo, chi]), or NULL.  Parallel over B*H, sequential over T.
 cudaError_t launch_bwd_prep(int T, int B, int H, int cell, float *zin, const float *zh,
-                            const float *c0, float *cs, float *ms, cudaStream_t s);
+                            const float *c0, float *cs, float *ms, cudaStream_t s,
+                            float *cr = nullptr, float clo = 0.f, float chi = 0.f);
 // dst[i] += src[i], i < n
 cudaError_t launch_add(float *dst, const float *src, size_t n, cudaStream_t s);
 // out[s][b][0..w) = in[t][b][col0 .. col0+w) with t = s, or, reversed,
@@ -175,6 +177,9 @@ struct BwdRecArgs {
   // [B] or NULL: steps t >= lengths[b] get zero gate gradients and pass the
   // carried gradients through (dh_n must then come in through dy, dhn NULL)
   const int32_t *lengths;
+  // LSTM cell clipping: the unclamped c_t [T*B][H] (NULL: none) and its bounds
+  const float *cr;
+  float clo, chi;
   float *DA, *DR, *dh0, *dc0;
   unsigned *ctr;  // zeroed before the launch
   int *err;

@@ -909,14 +909,66 @@ def test_backward_errors():
     with pytest.raises(RuntimeError, match="no rnn_backward"):
         binding.rnn_get_weight_grads(net.h, 0, None, None, None, None)
     net.close()
+    # projection clipping sits between W_hr and W_hh and breaks the folded
+    # projection recurrence: rejected (cell clipping is covered below)
+    spec = wl.LSTMP_2L.scaled(T=4, B=3, in_dim=6, hidden=12, proj=5, dtype="f32")
+    inp = wl.make_rnn_inputs(spec, seed=1)
     net = binding.RNN.from_spec(spec)
     net.set_weights(inp["weights"])
-    net.set_clip(binding.RCU_CLIP_CELL, (-1.0, 1.0))
+    net.set_clip(binding.RCU_CLIP_PROJ, (-1.0, 1.0))
     x = torch.zeros((spec.T, spec.B, spec.in_dim), device=dev)
     dy = torch.zeros((spec.T, spec.B, spec.Hout), device=dev)
-    with pytest.raises(RuntimeError, match="without clipping"):
+    with pytest.raises(RuntimeError, match="projection clipping"):
         binding.rnn_backward(net.h, spec.T, spec.B, x, None, None, None, dy, None, None, None, None,
                              None)
+    net.close()
+
+
+BWD_CLIP_SPECS = [
+    (wl.LSTM_T80.scaled(T=8, B=6, in_dim=12, hidden=20, layers=2, h0_std=0.5, c0_std=0.5),
+     (-0.12, 0.15)),
+    (wl.LSTMP_2L.scaled(T=7, B=5, in_dim=10, hidden=24, proj=8, dtype="f32", h0_std=0.5,
+                        c0_std=0.5), (-0.1, 0.12)),
+    (wl.BILSTM_VAR.scaled(T=9, B=7, in_dim=12, hidden=20, varlen=(1, 9), c0_std=0.5),
+     (-0.12, 0.15)),
+    (wl.LSTM_T80.scaled(T=24, B=16, in_dim=64, hidden=128, layers=1, c0_std=0.3),
+     (-0.1, 0.1)),
+]
+
+
+@pytest.mark.parametrize("spec,bounds", BWD_CLIP_SPECS,
+                         ids=lambda v: _bwd_id(v) if hasattr(v, "cell") else f"clip{v[1]}")
+def test_backward_cell_clip_parity(spec, bounds):
+    """Cell-state clipping in the backward pass (the clamp passes dc where the
+    unclamped cell value lies within the bounds) against the oracle with the
+    same clipping; bounds chosen so that a good share of the cells clamp."""
+    inp = wl.make_rnn_inputs(spec, seed=14)
+    g = torch.Generator().manual_seed(95)
+    L, B, H, Ho, D = spec.layers, spec.B, spec.hidden, spec.Hout, spec.D
+    dy = torch.randn((spec.T, B, D * Ho), generator=g)
+    dcn = torch.randn((L * D, B, H), generator=g)
+    dev = torch.device("cuda")
+    net = binding.RNN.from_spec(spec)
+    net.set_weights(inp["weights"])
+    net.set_clip(binding.RCU_CLIP_CELL, bounds)
+
+    def d(t):
+        return None if t is None else t.to(dev)
+    dx, dh0, dc0, grads = net.backward(d(inp["x"]), d(dy), lengths=d(inp["lengths"]),
+                                       h0=d(inp["h0"]), c0=d(inp["c0"]), dc_n=d(dcn))
+    torch.cuda.synchronize()
+    assert net.status() == 0
+    ref = oracle.rnn_backward(_cell(spec), inp["x"], inp["weights"], dy, hidden=H,
+                              proj=spec.proj, bidirectional=spec.bidir, lengths=inp["lengths"],
+                              h0=inp["h0"], c0=inp["c0"], dc_n=dcn, cell_clip=bounds)
+    pairs = [("dx", dx, ref["dx"]), ("dh0", dh0, ref["dh0"]), ("dc0", dc0, ref["dc0"])]
+    for i in range(L * D):
+        for k in ("w_ih", "w_hh", "b_ih", "b_hh") + (("w_hr",) if spec.proj else ()):
+            pairs.append((f"d{k}[{i}]", grads[i][k], ref["d" + k][i]))
+    for name, got, want in pairs:
+        e = _rel(got.cpu().numpy().astype(np.float64), want)
+        print(f"{name}: rel {e:.2e}")
+        assert e <= BWD_REL, f"{name}: relative max error {e:.3e}"
     net.close()
 
 
