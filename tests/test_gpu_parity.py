@@ -435,7 +435,7 @@ def test_backward_recurrence_timeout():
     """A CTA of the reverse-time kernel skips its first step arrival: the
     bounded counter wait runs out, the status reads RCU_ERR_TIMEOUT, and the
     next backward on the same handle is correct."""
-    spec = BWD_SPECS[1]
+    spec = wl.GRU_3L.scaled(T=6, B=9, in_dim=16, hidden=24, layers=2, dtype="f32")
     inp = wl.make_rnn_inputs(spec, seed=15)
     dy = torch.randn((spec.T, spec.B, spec.hidden), generator=torch.Generator().manual_seed(15))
     dev = torch.device("cuda")
@@ -450,7 +450,7 @@ def test_backward_recurrence_timeout():
     assert net.status() == 0
     ref = oracle.rnn_backward(oracle.GRU, inp["x"], inp["weights"], dy, hidden=spec.hidden,
                               h0=inp["h0"])
-    assert _rel(dx.cpu().numpy(), ref["dx"]) <= BWD_REL
+    assert _rel(dx.cpu().numpy(), ref["dx"]) <= 1e-4  # the backward parity bound
     net.close()
 
 
@@ -769,342 +769,3 @@ def test_full_size_sampled_rows(spec, rows):
         L = inp["lengths"].numpy()
         for b in range(spec.B):
             assert np.all(got[0][L[b]:, b] == 0.0)
-
-
-# ----------------------------------------------------------------------------- backward (BPTT)
-
-BWD_REL = 1e-4  # per tensor: max|gpu - ref| / max|ref| (fp32 sums over T*B terms, T steps)
-
-BWD_SPECS = [
-    wl.LSTM_T80.scaled(T=7, B=5, in_dim=12, hidden=20, layers=2, h0_std=0.5, c0_std=0.5),
-    wl.GRU_3L.scaled(T=6, B=9, in_dim=16, hidden=24, layers=2, dtype="f32"),
-    wl.GRU_3L.scaled(T=5, B=3, in_dim=7, hidden=13, layers=1, dtype="f32", h0_std=0.3),
-    wl.LSTM_T80.scaled(T=32, B=64, in_dim=256, hidden=512, layers=1),
-    wl.GRU_3L.scaled(T=24, B=32, in_dim=128, hidden=256, layers=3, dtype="f32", h0_std=0.1),
-    wl.LSTM_T80.scaled(T=1, B=1, in_dim=5, hidden=7, layers=2, c0_std=0.5, h0_std=0.5),
-    wl.GRU_3L.scaled(T=9, B=130, in_dim=40, hidden=48, layers=1, dtype="f32", h0_std=0.0),
-    # LSTM with projection
-    wl.LSTMP_2L.scaled(T=6, B=5, in_dim=12, hidden=20, proj=8, dtype="f32", h0_std=0.5,
-                       c0_std=0.5),
-    wl.LSTMP_2L.scaled(T=16, B=32, in_dim=64, hidden=128, proj=32, dtype="f32"),
-    # bidirectional
-    wl.BILSTM_VAR.scaled(T=7, B=5, in_dim=12, hidden=20, layers=2, varlen=None, h0_std=0.5,
-                         c0_std=0.5),
-    wl.GRU_3L.scaled(T=6, B=9, in_dim=16, hidden=24, layers=2, dtype="f32", bidir=True),
-    wl.LSTMP_2L.scaled(T=5, B=4, in_dim=8, hidden=16, proj=6, dtype="f32", bidir=True,
-                       h0_std=0.5),
-    wl.BILSTM_VAR.scaled(T=32, B=64, in_dim=256, hidden=256, varlen=None),
-    # variable lengths (length 1 and T both drawn)
-    wl.LSTM_T80.scaled(T=9, B=7, in_dim=12, hidden=20, layers=2, varlen=(1, 9), h0_std=0.5,
-                       c0_std=0.5),
-    wl.GRU_3L.scaled(T=8, B=9, in_dim=16, hidden=24, layers=2, dtype="f32", varlen=(1, 8),
-                     h0_std=0.3),
-    wl.BILSTM_VAR.scaled(T=10, B=6, in_dim=12, hidden=20, layers=2, varlen=(1, 10), h0_std=0.5,
-                         c0_std=0.5),
-    wl.GRU_3L.scaled(T=7, B=5, in_dim=9, hidden=11, layers=1, dtype="f32", bidir=True,
-                     varlen=(1, 7)),
-    wl.LSTMP_2L.scaled(T=7, B=5, in_dim=8, hidden=16, proj=6, dtype="f32", bidir=True,
-                       varlen=(1, 7), h0_std=0.5),
-    wl.BILSTM_VAR.scaled(T=40, B=64, in_dim=256, hidden=256, varlen=(5, 40)),
-]
-
-
-def _bwd_id(s):
-    return (f"{s.cell}-L{s.layers}-D{s.D}-T{s.T}-B{s.B}-H{s.hidden}-P{s.proj}"
-            + ("-varlen" if s.varlen else ""))
-
-
-def _rel(a, b):
-    return float(np.abs(a - b).max() / max(np.abs(b).max(), 1e-30))
-
-
-@pytest.mark.parametrize("spec", BWD_SPECS, ids=_bwd_id)
-def test_backward_parity(spec):
-    inp = wl.make_rnn_inputs(spec, seed=12)
-    g = torch.Generator().manual_seed(99)
-    L, B, H, Ho, D = spec.layers, spec.B, spec.hidden, spec.Hout, spec.D
-    dy = torch.randn((spec.T, B, D * Ho), generator=g)
-    dhn = torch.randn((L * D, B, Ho), generator=g)
-    dcn = torch.randn((L * D, B, H), generator=g) if spec.cell == "lstm" else None
-    dev = torch.device("cuda")
-    net = binding.RNN.from_spec(spec)
-    net.set_weights(inp["weights"])
-
-    def d(t):
-        return None if t is None else t.to(dev)
-    dx, dh0, dc0, grads = net.backward(d(inp["x"]), d(dy), lengths=d(inp["lengths"]),
-                                       h0=d(inp["h0"]), c0=d(inp["c0"]), dh_n=d(dhn),
-                                       dc_n=d(dcn))
-    torch.cuda.synchronize()
-    assert net.status() == 0
-    ref = oracle.rnn_backward(_cell(spec), inp["x"], inp["weights"], dy, hidden=H,
-                              proj=spec.proj, bidirectional=spec.bidir,
-                              lengths=inp["lengths"], h0=inp["h0"], c0=inp["c0"], dh_n=dhn,
-                              dc_n=dcn)
-    if inp["lengths"] is not None:  # no gradient reaches x past a row's end
-        dxc = dx.cpu().numpy()
-        for b, n in enumerate(inp["lengths"].tolist()):
-            assert np.all(dxc[n:, b] == 0.0)
-    pairs = [("dx", dx, ref["dx"]), ("dh0", dh0, ref["dh0"])]
-    if spec.cell == "lstm":
-        pairs.append(("dc0", dc0, ref["dc0"]))
-    for i in range(L * D):
-        for k in ("w_ih", "w_hh", "b_ih", "b_hh") + (("w_hr",) if spec.proj else ()):
-            pairs.append((f"d{k}[{i}]", grads[i][k], ref["d" + k][i]))
-    for name, got, want in pairs:
-        e = _rel(got.cpu().numpy().astype(np.float64), want)
-        print(f"{name}: rel {e:.2e}")
-        assert e <= BWD_REL, f"{name}: relative max error {e:.3e}"
-    net.close()
-
-
-BWD_BF16_SPECS = [
-    wl.GRU_3L.scaled(T=8, B=130, in_dim=64, hidden=96, layers=2),      # tensor-core forward
-    wl.LSTM_T80.scaled(T=9, B=6, in_dim=24, hidden=40, dtype="bf16", h0_std=0.5, c0_std=0.5),
-    wl.LSTMP_2L.scaled(T=7, B=5, in_dim=24, hidden=64, proj=16),        # folded forward
-    wl.LSTM_T80.scaled(T=9, B=6, in_dim=24, hidden=40, dtype="bf16", varlen=(1, 9)),
-]
-
-
-@pytest.mark.parametrize("spec", BWD_BF16_SPECS, ids=_bwd_id)
-def test_backward_bf16_parity(spec):
-    """bf16 handles: the fp32 gradient of the model with the bf16-rounded
-    weights the forward used, against the oracle with the same rounded
-    weights (bf16 tier: relative 2e-2; the forward's bf16 activation
-    rounding is in the recomputed states)."""
-    inp = wl.make_rnn_inputs(spec, seed=13)
-    g = torch.Generator().manual_seed(98)
-    L, B, Ho = spec.layers, spec.B, spec.Hout
-    dy = torch.randn((spec.T, B, Ho), generator=g)
-    dev = torch.device("cuda")
-    net = binding.RNN.from_spec(spec)
-    net.set_weights(inp["weights"])
-
-    def d(t):
-        return None if t is None else t.to(dev)
-    dx, dh0, dc0, grads = net.backward(d(inp["x"]), d(dy), lengths=d(inp["lengths"]),
-                                       h0=d(inp["h0"]), c0=d(inp["c0"]))
-    torch.cuda.synchronize()
-    assert net.status() == 0
-    ref = oracle.rnn_backward(_cell(spec), inp["x"], inp["weights"], dy, hidden=spec.hidden,
-                              proj=spec.proj, lengths=inp["lengths"], h0=inp["h0"],
-                              c0=inp["c0"], bf16_weights=True)
-    pairs = [("dx", dx, ref["dx"]), ("dh0", dh0, ref["dh0"])]
-    for i in range(L):
-        for k in ("w_ih", "w_hh", "b_ih") + (("w_hr",) if spec.proj else ()):
-            pairs.append((f"d{k}[{i}]", grads[i][k], ref["d" + k][i]))
-    for name, got, want in pairs:
-        e = _rel(got.cpu().numpy().astype(np.float64), want)
-        print(f"{name}: rel {e:.2e}")
-        assert e <= BF16_REL, f"{name}: relative max error {e:.3e}"
-    net.close()
-
-
-def test_backward_errors():
-    spec = BWD_SPECS[0]
-    inp = wl.make_rnn_inputs(spec, seed=1)
-    dev = torch.device("cuda")
-    net = binding.RNN.from_spec(spec)
-    net.set_weights(inp["weights"])
-    with pytest.raises(RuntimeError, match="no rnn_backward"):
-        binding.rnn_get_weight_grads(net.h, 0, None, None, None, None)
-    net.close()
-    # projection clipping sits between W_hr and W_hh and breaks the folded
-    # projection recurrence: rejected (cell clipping is covered below)
-    spec = wl.LSTMP_2L.scaled(T=4, B=3, in_dim=6, hidden=12, proj=5, dtype="f32")
-    inp = wl.make_rnn_inputs(spec, seed=1)
-    net = binding.RNN.from_spec(spec)
-    net.set_weights(inp["weights"])
-    net.set_clip(binding.RCU_CLIP_PROJ, (-1.0, 1.0))
-    x = torch.zeros((spec.T, spec.B, spec.in_dim), device=dev)
-    dy = torch.zeros((spec.T, spec.B, spec.Hout), device=dev)
-    with pytest.raises(RuntimeError, match="projection clipping"):
-        binding.rnn_backward(net.h, spec.T, spec.B, x, None, None, None, dy, None, None, None, None,
-                             None)
-    net.close()
-
-
-BWD_CLIP_SPECS = [
-    (wl.LSTM_T80.scaled(T=8, B=6, in_dim=12, hidden=20, layers=2, h0_std=0.5, c0_std=0.5),
-     (-0.12, 0.15)),
-    (wl.LSTMP_2L.scaled(T=7, B=5, in_dim=10, hidden=24, proj=8, dtype="f32", h0_std=0.5,
-                        c0_std=0.5), (-0.1, 0.12)),
-    (wl.BILSTM_VAR.scaled(T=9, B=7, in_dim=12, hidden=20, varlen=(1, 9), c0_std=0.5),
-     (-0.12, 0.15)),
-    (wl.LSTM_T80.scaled(T=24, B=16, in_dim=64, hidden=128, layers=1, c0_std=0.3),
-     (-0.1, 0.1)),
-]
-
-
-@pytest.mark.parametrize("spec,bounds", BWD_CLIP_SPECS,
-                         ids=lambda v: _bwd_id(v) if hasattr(v, "cell") else f"clip{v[1]}")
-def test_backward_cell_clip_parity(spec, bounds):
-    """Cell-state clipping in the backward pass (the clamp passes dc where the
-    unclamped cell value lies within the bounds) against the oracle with the
-    same clipping; bounds chosen so that a good share of the cells clamp."""
-    inp = wl.make_rnn_inputs(spec, seed=14)
-    g = torch.Generator().manual_seed(95)
-    L, B, H, Ho, D = spec.layers, spec.B, spec.hidden, spec.Hout, spec.D
-    dy = torch.randn((spec.T, B, D * Ho), generator=g)
-    dcn = torch.randn((L * D, B, H), generator=g)
-    dev = torch.device("cuda")
-    net = binding.RNN.from_spec(spec)
-    net.set_weights(inp["weights"])
-    net.set_clip(binding.RCU_CLIP_CELL, bounds)
-
-    def d(t):
-        return None if t is None else t.to(dev)
-    dx, dh0, dc0, grads = net.backward(d(inp["x"]), d(dy), lengths=d(inp["lengths"]),
-                                       h0=d(inp["h0"]), c0=d(inp["c0"]), dc_n=d(dcn))
-    torch.cuda.synchronize()
-    assert net.status() == 0
-    ref = oracle.rnn_backward(_cell(spec), inp["x"], inp["weights"], dy, hidden=H,
-                              proj=spec.proj, bidirectional=spec.bidir, lengths=inp["lengths"],
-                              h0=inp["h0"], c0=inp["c0"], dc_n=dcn, cell_clip=bounds)
-    pairs = [("dx", dx, ref["dx"]), ("dh0", dh0, ref["dh0"]), ("dc0", dc0, ref["dc0"])]
-    for i in range(L * D):
-        for k in ("w_ih", "w_hh", "b_ih", "b_hh") + (("w_hr",) if spec.proj else ()):
-            pairs.append((f"d{k}[{i}]", grads[i][k], ref["d" + k][i]))
-    for name, got, want in pairs:
-        e = _rel(got.cpu().numpy().astype(np.float64), want)
-        print(f"{name}: rel {e:.2e}")
-        assert e <= BWD_REL, f"{name}: relative max error {e:.3e}"
-    net.close()
-
-
-# ----------------------------------------------------------------------------- RSSM backward
-
-RSSM_BWD_SPECS = [
-    wl.RSSM_B50,
-    wl.RSSM_B50.scaled(T=7, B=3, state_dim=5, action_dim=0, hidden=33, rnn_hidden=17,
-                       state0_std=1.0, belief0_std=0.5),
-    wl.RSSM_B50.scaled(T=6, B=70, state_dim=13, action_dim=5, hidden=72, rnn_hidden=40,
-                       state0_std=1.0, belief0_std=0.5),
-]
-
-
-@pytest.mark.parametrize("spec", RSSM_BWD_SPECS,
-                         ids=lambda s: f"T{s.T}-B{s.B}-S{s.state_dim}-A{s.action_dim}-H{s.hidden}")
-@pytest.mark.parametrize("which", ["all", "beliefs_only"])
-def test_rssm_backward_parity(spec, which):
-    """rssm_backward + rssm_get_weight_grads against the oracle's RSSM backward
-    (per tensor: max|gpu - ref| / max|ref| <= 1e-4); gradients given for every
-    output, or for the beliefs alone (the others NULL)."""
-    inp = wl.make_rssm_inputs(spec, seed=22)
-    g = torch.Generator().manual_seed(97)
-    T, B, S, RH = spec.T, spec.B, spec.state_dim, spec.rnn_hidden
-    grads = {k: torch.randn((T, B, n), generator=g)
-             for k, n in (("dmeans", S), ("dstds", S), ("dstates", S), ("dbeliefs", RH))}
-    if which == "beliefs_only":
-        grads = {"dbeliefs": grads["dbeliefs"]}
-    dev = torch.device("cuda")
-    m = binding.RSSM(spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden)
-    m.set_weights(inp["weights"])
-    with pytest.raises(RuntimeError, match="no rssm_backward"):
-        binding.rssm_get_weight_grads(m.h, {})
-    d = lambda t: None if t is None else t.to(dev)
-    dstate0, dbelief0, dactions, wg = m.backward(
-        d(inp["actions"]), d(inp["eps"]), d(inp["state0"]), d(inp["belief0"]),
-        **{k: d(v) for k, v in grads.items()})
-    torch.cuda.synchronize()
-    assert binding.rssm_get_status(m.h) == 0
-    ref = oracle.rssm_backward(inp["weights"], inp["actions"], inp["eps"], state0=inp["state0"],
-                               belief0=inp["belief0"], **grads)
-    pairs = [("dstate0", dstate0), ("dbelief0", dbelief0)]
-    if spec.action_dim > 0:
-        pairs.append(("dactions", dactions))
-    pairs += [("d" + k, wg[k]) for k in binding.RSSM_WEIGHT_NAMES]
-    for name, got in pairs:
-        e = _rel(got.cpu().numpy().astype(np.float64), ref[name])
-        print(f"{name}: rel {e:.2e}")
-        assert e <= BWD_REL, f"{name}: relative max error {e:.3e}"
-    m.close()
-
-
-@pytest.mark.parametrize("spec", [
-    wl.RSSM_ACTOR,
-    wl.RSSM_B50.scaled(T=6, B=70, state_dim=13, action_dim=5, hidden=72, rnn_hidden=40,
-                       state0_std=1.0, belief0_std=0.5, actor_hidden=37),
-], ids=lambda s: f"T{s.T}-B{s.B}-S{s.state_dim}-A{s.action_dim}-X{s.actor_hidden}")
-def test_rssm_actor_backward_parity(spec):
-    """rssm_backward_actor + rssm_get_weight_grads + rssm_get_actor_grads
-    against the oracle's backward of the actor variant (per tensor: max|gpu -
-    ref| / max|ref| <= 1e-4), including the gradient reaching each action."""
-    inp = wl.make_rssm_inputs(spec, seed=24)
-    g = torch.Generator().manual_seed(96)
-    T, B, S, RH = spec.T, spec.B, spec.state_dim, spec.rnn_hidden
-    grads = {k: torch.randn((T, B, n), generator=g)
-             for k, n in (("dmeans", S), ("dstds", S), ("dstates", S), ("dbeliefs", RH))}
-    dev = torch.device("cuda")
-    m = binding.RSSM(spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden)
-    m.set_weights(inp["weights"])
-    m.set_actor(inp["actor"])
-    with pytest.raises(RuntimeError, match="no rssm_backward_actor"):
-        binding.rssm_get_actor_grads(m.h, {})
-    d = lambda t: None if t is None else t.to(dev)
-    dstate0, dbelief0, dactions, wg, ag = m.backward_actor(
-        d(inp["eps"]), d(inp["state0"]), d(inp["belief0"]), **{k: d(v) for k, v in grads.items()})
-    torch.cuda.synchronize()
-    assert binding.rssm_get_status(m.h) == 0
-    ref = oracle.rssm_backward(inp["weights"], None, inp["eps"], state0=inp["state0"],
-                               belief0=inp["belief0"], actor=inp["actor"], **grads)
-    pairs = [("dstate0", dstate0), ("dbelief0", dbelief0), ("dactions", dactions)]
-    pairs += [("d" + k, wg[k]) for k in binding.RSSM_WEIGHT_NAMES]
-    pairs += [("d" + k, ag[k]) for k in binding.RSSM_ACTOR_NAMES]
-    for name, got in pairs:
-        e = _rel(got.cpu().numpy().astype(np.float64), ref[name])
-        print(f"{name}: rel {e:.2e}")
-        assert e <= BWD_REL, f"{name}: relative max error {e:.3e}"
-    m.close()
-
-
-def test_rssm_profile_phases():
-    """RCU_ATTR_PROFILE on an RSSM handle times the unroll and the three phases
-    of rssm_backward, once per call each."""
-    spec = wl.RSSM_B50.scaled(T=5, B=4)
-    inp = wl.make_rssm_inputs(spec, seed=23)
-    dev = torch.device("cuda")
-    m = binding.RSSM(spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden)
-    m.set_weights(inp["weights"])
-    m.set_attr(binding.RCU_ATTR_PROFILE, 1)
-    binding.rssm_profile_reset(m.h)
-    m.backward(inp["actions"].to(dev), inp["eps"].to(dev),
-               dbeliefs=torch.ones((spec.T, spec.B, spec.rnn_hidden), device=dev))
-    prof = m.profile()
-    assert binding.rssm_get_status(m.h) == 0
-    for name in ("rssm_unroll", "rssm_bwd_recompute", "rssm_bwd_chain", "rssm_bwd_grads"):
-        assert name in prof and prof[name][1] == 1 and prof[name][0] > 0.0, (name, prof)
-    assert m.launch_count() > 4 * spec.T
-    m.close()
-
-
-# ----------------------------------------------------------------------------- full-size training pass
-
-@pytest.mark.parametrize("spec", [wl.LSTM_TRAIN, wl.BILSTM_TRAIN], ids=lambda s: s.name)
-def test_training_pass_full_size(spec):
-    """The training workloads at their full size, through rnn_backward as the
-    benchmark calls it (seed-0 inputs, the workload's dy, no dh_n / dc_n):
-    every gradient tensor against the oracle's backward over all rows."""
-    inp = wl.make_rnn_inputs(spec, seed=0)
-    dev = torch.device("cuda")
-    net = binding.RNN.from_spec(spec)
-    net.set_weights(inp["weights"])
-    d = lambda t: None if t is None else t.to(dev)
-    dx, dh0, dc0, grads = net.backward(d(inp["x"]), d(inp["dy"]), lengths=d(inp["lengths"]),
-                                       h0=d(inp["h0"]), c0=d(inp["c0"]))
-    torch.cuda.synchronize()
-    assert net.status() == 0
-    ref = oracle.rnn_backward(_cell(spec), inp["x"], inp["weights"], inp["dy"],
-                              hidden=spec.hidden, proj=spec.proj, bidirectional=spec.bidir,
-                              lengths=inp["lengths"], h0=inp["h0"], c0=inp["c0"])
-    pairs = [("dx", dx, ref["dx"]), ("dh0", dh0, ref["dh0"])]
-    if spec.cell == "lstm":
-        pairs.append(("dc0", dc0, ref["dc0"]))
-    for i in range(spec.layers * spec.D):
-        for k in ("w_ih", "w_hh", "b_ih", "b_hh"):
-            pairs.append((f"d{k}[{i}]", grads[i][k], ref["d" + k][i]))
-    for name, got, want in pairs:
-        e = _rel(got.cpu().numpy().astype(np.float64), want)
-        print(f"{name}: rel {e:.2e}")
-        assert e <= BWD_REL, f"{name}: relative max error {e:.3e}"
-    net.close()
