@@ -387,7 +387,8 @@ __global__ void add_kernel(float *__restrict__ dst, const float *__restrict__ sr
 }  // namespace
 
 namespace {
-// out[s][b][c] = in[t][b][col0 + c], t = reverse ? T-1-s : s (row stride ldi)
+// out[s][b][c] = in[t][b][col0 + c] (row stride ldi), t = s, or reversed
+// within the row's length: t = len_b-1-s for s < len_b, t = s past it
 __global__ void gather_steps_kernel(const float *__restrict__ in, int ldi, int col0, int w, int T,
                                     int B, int reverse, const int32_t *__restrict__ lengths,
                                     float *__restrict__ out) {
