@@ -131,3 +131,23 @@ def test_binding_signatures_match_the_header():
         assert (res is ctypes.c_char_p) == ("char" in ret), name
         if "char" not in ret:
             assert res is ctypes.c_int and ret == "int", name
+
+
+def test_null_handle_errors_reach_rcu_last_error(lib):
+    """Argument errors from both halves of the host code (stacked networks,
+    RSSM) return RCU_ERR_INVALID and leave their message for rcu_last_error on
+    this thread; a NULL handle is checked before any CUDA call, so this runs
+    without a GPU."""
+    sigs = binding.signatures()
+    for name in ("rnn_get_weight_grads", "rnn_set_attr", "rnn_profile_entry",
+                 "rssm_get_weight_grads", "rssm_get_actor_grads", "rssm_set_attr",
+                 "rssm_profile_entry", "rssm_backward", "rssm_backward_actor"):
+        fn = getattr(lib, name)
+        res, args = sigs[name]
+        fn.restype, fn.argtypes = res, args
+        zeros = [None if a is not ctypes.c_int and a is not ctypes.c_int64 else 0 for a in args]
+        rc = fn(*zeros)
+        assert rc == binding.RCU_ERR_INVALID, (name, rc)
+        lib.rcu_last_error.restype = ctypes.c_char_p
+        msg = lib.rcu_last_error().decode()
+        assert name.split("_", 1)[0] in msg and "NULL handle" in msg, (name, msg)
