@@ -333,6 +333,35 @@ def test_rssm_profile_phases():
     m.close()
 
 
+def test_backward_argument_errors():
+    """Degenerate arguments are rejected on the host before any launch: an
+    empty sequence or batch, a missing actor, missing actions."""
+    spec = wl.LSTM_T80.scaled(T=3, B=2, in_dim=4, hidden=5)
+    inp = wl.make_rnn_inputs(spec, seed=3)
+    dev = torch.device("cuda")
+    net = binding.RNN.from_spec(spec)
+    net.set_weights(inp["weights"])
+    x = torch.zeros((3, 2, 4), device=dev)
+    dy = torch.zeros((3, 2, 5), device=dev)
+    for T, B in ((0, 2), (3, 0)):
+        with pytest.raises(RuntimeError, match="need T, B >= 1"):
+            binding.rnn_backward(net.h, T, B, x, None, None, None, dy, None, None, None, None, None)
+    net.close()
+    rs = wl.RSSM_B50.scaled(T=3, B=2, state_dim=4, action_dim=2, hidden=6, rnn_hidden=5)
+    ri = wl.make_rssm_inputs(rs, seed=3)
+    m = binding.RSSM(rs.state_dim, rs.action_dim, rs.hidden, rs.rnn_hidden)
+    m.set_weights(ri["weights"])
+    eps = ri["eps"].to(dev)
+    with pytest.raises(RuntimeError, match="actor not set"):
+        m.backward_actor(eps)
+    with pytest.raises(RuntimeError, match="need T, B >= 1"):
+        m.backward(None, eps)  # actions missing with action_dim > 0
+    with pytest.raises(RuntimeError, match="need T, B >= 1"):
+        binding.rssm_backward(m.h, 0, 2, None, None, ri["actions"].to(dev), eps, None, None, None,
+                              None, None, None, None)
+    m.close()
+
+
 # ----------------------------------------------------------------------------- full-size training pass
 
 @pytest.mark.parametrize("spec", [wl.LSTM_TRAIN, wl.BILSTM_TRAIN], ids=lambda s: s.name)
