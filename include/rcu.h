@@ -80,10 +80,6 @@ typedef struct rcu_rssm_s *rcu_rssm_t;
                                          3 = cluster-resident recurrent kernel where W_hh
                                          fits one thread-block cluster (else SIMT) */
 #define RCU_ATTR_TRACE 5              /* 1 = record per-step timestamps (rnn_get_trace) */
-#define RCU_ATTR_TC_CLUSTER 6         /* tensor-core recurrent kernel: CTAs per thread-block
-                                         cluster that share each h tile by TMA multicast
-                                         (0 or 1 = none, 2, 4, 8; used when it divides the
-                                         number of unit groups) */
 #define RCU_ATTR_TC_KSPLIT 7          /* tensor-core recurrent kernel: CTAs that split the
                                          K (= hidden) dimension of h W_hh^T, exchanging
                                          partial sums through distributed shared memory

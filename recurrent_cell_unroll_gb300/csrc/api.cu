@@ -78,7 +78,6 @@ struct rcu_rnn_s : EventProfiler {
   int64_t timeout_ns = 2000000000LL;
   int drop_arrival = 0;
   int force_path = 0;
-  int tc_cluster = 0;  // CTAs per cluster sharing h loads in the tensor-core recurrent kernel
   int tc_ksplit = 0;   // CTAs splitting K in the tensor-core recurrent kernel (0 = automatic)
   // LSTM clipping (rnn_set_clip)
   int cclip = 0, pclip = 0;
@@ -226,11 +225,6 @@ extern "C" int rnn_set_attr(rcu_rnn_t h, int attr, int64_t value) {
       return RCU_OK;
     case RCU_ATTR_PROFILE:
       h->profile = value != 0;
-      return RCU_OK;
-    case RCU_ATTR_TC_CLUSTER:
-      if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8)
-        return fail(RCU_ERR_INVALID, "cluster size must be 0, 1, 2, 4 or 8");
-      h->tc_cluster = (int)value;
       return RCU_OK;
     case RCU_ATTR_TC_KSPLIT:
       if (value != 0 && value != 1 && value != 2 && value != 4)
@@ -624,7 +618,6 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
       CU(cudaMemsetAsync(h->hx2, 0, (size_t)D * 2 * B * ldH * 2, s));
       TcRecParams tp;
       tp.base = pf;
-      tp.cluster = h->tc_cluster;
       tp.ksplit = h->tc_ksplit;
       for (int d = 0; d < D; ++d) tp.Wtc[d] = h->lw[(size_t)l * D + d].fold_w.p;
       h->begin("recurrent_tc_lstmp", s);
@@ -676,7 +669,6 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
     if (tc_rec) {
       TcRecParams tp;
       tp.base = p;
-      tp.cluster = h->tc_cluster;
       tp.ksplit = h->tc_ksplit;
       for (int d = 0; d < D; ++d) tp.Wtc[d] = h->lw[(size_t)l * D + d].tc_whh.p;
       cudaError_t e = launch_tc_recurrent(tp, h->nsm, s);

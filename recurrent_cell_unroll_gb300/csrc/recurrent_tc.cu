@@ -155,17 +155,11 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
   const unsigned n_wait = (unsigned)NU;
   // steps this batch group runs: the longest row of the group (rows sorted by length)
   const int Tg = row0 < B ? p.meta.lens_sorted[row0] : 0;
-  // without a K split, an optional cluster of CTAs sharing (d, bg): each
-  // issues 1/cs of the h k-blocks as multicast loads into every member; a
-  // stage is free again once all members' MMAs have consumed it
-  const uint32_t cs = KS > 1 ? 1u : tc::cluster_nctarank();
-  const uint32_t crank = KS > 1 ? 0u : tc::cluster_ctarank();
-  const uint16_t cmask = (uint16_t)((1u << cs) - 1u);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STG; ++s) {
       tc::mbar_init(&ctl->full[s], 1);
-      tc::mbar_init(&ctl->empty[s], cs);
+      tc::mbar_init(&ctl->empty[s], 1);
     }
     tc::mbar_init(&ctl->wbar, 1);
     tc::mbar_init(&ctl->tfull, 1);
@@ -181,8 +175,8 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
   if (warp == 1) tc::tmem_alloc(&ctl->tmem_base, TCOLS);
   tc::tc_fence_before();
   __syncthreads();
-  // peers' barriers exist before any multicast load or partial-sum store
-  if (cs > 1 || KS > 1) tc::cluster_sync();
+  // the partner's barriers exist before any partial-sum store
+  if (KS > 1) tc::cluster_sync();
   tc::tc_fence_after();
   const uint32_t tbase = ctl->tmem_base;
   int x_left = 0;  // K split, thread 64: phases consumed (negated - 1 if one more is armed)
@@ -226,13 +220,8 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
           const int kb = kb0 + i;
           if (!tc::mbar_wait(&ctl->empty[stage], phase ^ 1, p.err, abort, tmo)) goto producer_out;
           tc::mbar_arrive_expect_tx(&ctl->full[stage], (uint32_t)(maps.a_rows * BK * 2));
-          if (cs == 1) {
-            tc::tma_load_2d(sA + (size_t)stage * A_STAGE, &maps.hx, &ctl->full[stage], kb * BK,
-                            arow);
-          } else if ((uint32_t)kb % cs == crank) {
-            tc::tma_load_2d_mc(sA + (size_t)stage * A_STAGE, &maps.hx, &ctl->full[stage],
-                               kb * BK, arow, cmask);
-          }
+          tc::tma_load_2d(sA + (size_t)stage * A_STAGE, &maps.hx, &ctl->full[stage], kb * BK,
+                          arow);
           pend_stage[npend % MAX_STAGES] = stage;
           pend_phase[npend % MAX_STAGES] = phase;
           ++npend;
@@ -286,15 +275,7 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
             }
           }
           const uint64_t ad = adesc0 + (uint64_t)(stage * (A_STAGE >> 4));
-          if (cs == 1) {
-            tc::mma4_bf16_commit(tbase, ad, bd, idesc, i != 0, &ctl->empty[stage]);
-          } else {
-            tc::mma_bf16(tbase, ad, bd, idesc, i != 0);
-            tc::mma_bf16(tbase, ad + 2, bd + 2, idesc, 1u);
-            tc::mma_bf16(tbase, ad + 4, bd + 4, idesc, 1u);
-            tc::mma_bf16(tbase, ad + 6, bd + 6, idesc, 1u);
-            tc::mma_commit_mc(&ctl->empty[stage], cmask);
-          }
+          tc::mma4_bf16_commit(tbase, ad, bd, idesc, i != 0, &ctl->empty[stage]);
           if (tr) cyc_issue += clock64() - c1;
           if (++stage == STG) { stage = 0; phase ^= 1; }
         }
@@ -521,9 +502,8 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
   }
   tc::tc_fence_before();
   __syncthreads();
-  // no member leaves while a peer may still deliver loads, partial sums or
-  // arrivals to it
-  if (cs > 1 || KS > 1) tc::cluster_sync();
+  // no member leaves while its partner may still deliver partial sums to it
+  if (KS > 1) tc::cluster_sync();
   if (KS > 1 && threadIdx.x == 64) {
     // After an early exit a peer may have sent one step more than this CTA
     // consumed (never two: the peer's next step needs this CTA's arrival at
@@ -549,7 +529,7 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
   }
 }
 
-// K kept whole (optionally with a multicast cluster chosen at launch)
+// K kept whole
 template <int NG>
 __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ Maps maps,
                                                        const RecParams p) {
@@ -643,44 +623,28 @@ bool ks_fits(int nG, int K, int ks) {
   return g.stages >= 2 && (ks - 1) * g.nkbm < g.nkb;
 }
 
-// Cooperative launch of `grid` CTAs in clusters of `cs`; false (nothing
-// launched) when that cluster grid cannot be resident at once.  `fixed`: the
-// kernel declares its cluster shape itself (then no launch attribute names it).
+// Cooperative launch of `grid` CTAs of a kernel that declares its cluster
+// shape (`cs` CTAs) itself; false (nothing launched) when that cluster grid
+// cannot be resident at once.
 bool launch_clustered(const void *fn, int grid, int cs, size_t smem, void **args, cudaStream_t s,
-                      cudaError_t *err, bool fixed = false) {
+                      cudaError_t *err) {
   *err = cudaSuccess;
-  if (!fixed &&
-      cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(NT);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cs;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeCooperative;
-  attr[1].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
   int max_clusters = 0;
-  cudaLaunchConfig_t q = cfg;
-  q.numAttrs = 1;  // occupancy query on the cluster shape
-  if (fixed) q.numAttrs = 0;
-  if (cudaOccupancyMaxActiveClusters(&max_clusters, fn, &q) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveClusters(&max_clusters, fn, &cfg) != cudaSuccess ||
       (long long)max_clusters * cs < grid) {
     cudaGetLastError();
     return false;
   }
-  if (fixed) {  // cooperative attribute only; the cluster shape is the kernel's
-    attr[0] = attr[1];
-    cfg.numAttrs = 1;
-  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   *err = cudaLaunchKernelExC(&cfg, fn, args);
   return true;
 }
@@ -699,10 +663,9 @@ cudaError_t launch_tc_recurrent(const TcRecParams &tp, int nsm, cudaStream_t s) 
     return cudaErrorInvalidValue;
 
   // K split over ks CTAs (a cluster): requested (1, 2 or 4), or automatic (a
-  // pair) when no multicast cluster was asked for; halved until the plan fits
-  // shared memory and gives every CTA a K block
+  // pair); halved until the plan fits shared memory and gives every CTA a K block
   int ks = tp.ksplit;
-  if (ks == 0) ks = tp.cluster > 1 ? 1 : 2;
+  if (ks == 0) ks = 2;
   while (ks > 1 && !ks_fits(nG, p.Hout, ks)) ks /= 2;
 
   for (int attempt = 0; attempt < 3; ++attempt) {
@@ -720,17 +683,11 @@ cudaError_t launch_tc_recurrent(const TcRecParams &tp, int nsm, cudaStream_t s) 
     const int grid = p.D * NBG * p.NU;
     void *args[] = {&maps, &p};
     if (ks > 1) {
-      if (launch_clustered(fn, grid, ks, geo.smem, args, s, &e, true)) return e;
+      if (launch_clustered(fn, grid, ks, geo.smem, args, s, &e)) return e;
       ks /= 2;  // that cluster grid cannot be co-resident: a smaller split
       while (ks > 1 && !ks_fits(nG, p.Hout, ks)) ks /= 2;
       continue;
     }
-    // optional multicast cluster: the requested size, halved until it divides
-    // the unit groups.  Multicast was measured not to pay on GB300 for this
-    // kernel, so it is opt-in.
-    int cs = tp.cluster > 0 ? tp.cluster : 1;
-    while (cs > 1 && (p.NU % cs) != 0) cs /= 2;
-    if (cs > 1 && launch_clustered(fn, grid, cs, geo.smem, args, s, &e)) return e;
     return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(NT), args, geo.smem, s);
   }
   return cudaErrorInvalidConfiguration;

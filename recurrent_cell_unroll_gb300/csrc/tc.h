@@ -23,7 +23,6 @@ cudaError_t launch_tc_gemm(const __nv_bfloat16 *X, int ldx, const __nv_bfloat16 
 struct TcRecParams {
   RecParams base;
   const void *Wtc[2];  // tensor-core packed W_hh per direction (tc_pack_whh)
-  int cluster = 0;     // CTAs per cluster sharing h loads by multicast (0 = automatic)
   int ksplit = 0;      // CTAs splitting K: 0 = automatic (2), 1 = none, 2 or 4 = a cluster
 };
 // weights can be packed for the tensor-core kernel (shape only)

@@ -92,17 +92,6 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
       "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
-// Same load delivered to the shared memory (same offset) of every CTA of the
-// cluster in `mask`; each destination's mbarrier at `bar`'s offset receives
-// the byte count.
-__device__ __forceinline__ void tma_load_2d_mc(void *smem_dst, const CUtensorMap *map,
-                                               uint64_t *bar, int x, int y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(mask)
-      : "memory");
-}
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -232,16 +221,6 @@ __device__ __forceinline__ void mma4_bf16_commit(uint32_t tmem_d, uint64_t adesc
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t}" ::"r"(
           tmem_d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Arrive once on the mbarrier at `bar`'s offset in every CTA of `mask` when
-// all previously issued tcgen05.mma of this thread complete.
-__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(mask)
       : "memory");
 }
 

@@ -226,23 +226,6 @@ def test_barrier_wait_times_out_and_context_survives():
     net.close()
 
 
-@pytest.mark.parametrize("cluster", [2, 4])
-def test_tensor_core_multicast_clusters(cluster):
-    """h tiles shared within a thread-block cluster by TMA multicast."""
-    spec = wl.GRU_3L.scaled(layers=2, T=11, B=200, in_dim=48, hidden=128, varlen=(1, 11))
-    inp = wl.make_rnn_inputs(spec, seed=15)
-    dev = torch.device("cuda")
-    net = binding.RNN.from_spec(spec)
-    net.set_attr(binding.RCU_ATTR_TC_CLUSTER, cluster)
-    net.set_weights(inp["weights"])
-    y, hn, _ = net.forward(inp["x"].to(dev), lengths=inp["lengths"].to(dev),
-                           h0=inp["h0"].to(dev))
-    assert net.status() == 0
-    ref = run_oracle(spec, inp)
-    compare(spec, (y.cpu().numpy(), hn.cpu().numpy(), None), ref)
-    net.close()
-
-
 KSPLIT = [
     # two batch groups with a ragged tail; 13 sixteen-unit tiles (odd: the last
     # pair has one tile of zero rows); H not a multiple of 16
