@@ -57,7 +57,10 @@ struct Ctl {
   int abort;
   int go;   // epilogue: result of the per-step accumulator wait, shared by all its threads
   int go2;  // epilogue: result of the per-step partial-sum wait (K split)
-  uint32_t x_sent;  // K split: steps whose partial sums this CTA has sent to its peer
+  // K split: peer_sent[r] = steps whose partial sums CTA rank r of the
+  // cluster sent to this CTA, stored here by rank r itself before the final
+  // cluster barrier
+  uint32_t peer_sent[4];
 };
 
 // KS = CTAs splitting K (a cluster of KS CTAs computes the gate
@@ -169,7 +172,7 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
     // byte count, completed by the peer's asynchronous stores
     tc::mbar_init(&ctl->xfull, 1);
     ctl->abort = 0;
-    ctl->x_sent = 0;
+    for (int i = 0; i < 4; ++i) ctl->peer_sent[i] = 0;
     tc::fence_mbar_init();
   }
   if (warp == 1) tc::tmem_alloc(&ctl->tmem_base, TCOLS);
@@ -180,6 +183,7 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
   tc::tc_fence_after();
   const uint32_t tbase = ctl->tmem_base;
   int x_left = 0;  // K split, thread 64: phases consumed (negated - 1 if one more is armed)
+  uint32_t x_sent = 0;  // K split, thread 64: steps whose partial sums this CTA has sent
 
   if (warp == 0) {
     if (lane == 0) {
@@ -407,7 +411,7 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
                               __uint_as_float(rp[i][gi][2]), __uint_as_float(rp[i][gi][3]),
                               peer_bar[i]);
             }
-          if (threadIdx.x == 64) ctl->x_sent = (uint32_t)(step + 1);
+          if (threadIdx.x == 64) x_sent = (uint32_t)(step + 1);
         }
       }
       if (p.trace && blockIdx.x == 0 && threadIdx.x == 64) p.trace[step * 16 + 5] = globaltimer_ns();
@@ -502,19 +506,33 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
   }
   tc::tc_fence_before();
   __syncthreads();
-  // no member leaves while its partner may still deliver partial sums to it
+  if (KS > 1 && threadIdx.x == 64) {
+    // Tell every peer how many steps of partial sums it will have received
+    // from this CTA.  The count is stored into the peer's shared memory now,
+    // while the peer is certain to be resident (it cannot pass the cluster
+    // barrier below before this CTA arrives), so that nothing after that
+    // barrier touches another CTA's shared memory: a peer may exit as soon as
+    // it has passed it.
+    for (int pr = 0; pr < KS; ++pr) {
+      if (pr == kr) continue;
+      const uint32_t dst = tc::mapa_shared(tc::smem_u32(&ctl->peer_sent[kr]), (uint32_t)pr);
+      asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(dst), "r"(x_sent) : "memory");
+    }
+  }
+  // no member leaves while its partner may still deliver partial sums to it;
+  // the barrier's release/acquire also makes the peers' counts visible here
   if (KS > 1) tc::cluster_sync();
   if (KS > 1 && threadIdx.x == 64) {
     // After an early exit a peer may have sent one step more than this CTA
     // consumed (never two: the peer's next step needs this CTA's arrival at
     // the step barrier, made only after consuming).  Those stores land in this
-    // CTA's shared memory, so wait for them (bounded) before leaving.
+    // CTA's shared memory, so wait for them (bounded) before leaving.  Only
+    // this CTA's own shared memory is read here.
     const int done = x_left < 0 ? -x_left - 1 : x_left;
     uint32_t peer_sent = 0;
     for (int pr = 0; pr < KS; ++pr) {
       if (pr == kr) continue;
-      const uint32_t v =
-          tc::ld_cluster_u32(tc::mapa_shared(tc::smem_u32(&ctl->x_sent), (uint32_t)pr));
+      const uint32_t v = *reinterpret_cast<volatile uint32_t *>(&ctl->peer_sent[pr]);
       peer_sent = v > peer_sent ? v : peer_sent;
     }
     if ((int)peer_sent > done) {

@@ -123,11 +123,6 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, flo
       "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
       : "memory");
 }
-__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
