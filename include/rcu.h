@@ -308,9 +308,10 @@ RCU_API int rnn_destroy(rcu_rnn_t h);
  * cudaMalloc themselves or have the library do it: code embedded in a host
  * framework that owns the device heap, processes whose device-memory budget
  * is fixed before they start, and loops that cannot afford an allocation
- * (it may synchronise the device or fail under memory pressure).  The paper
- * has no counterpart to this entry point; it computes the same LSTM as
- * rnn_forward with cell RCU_LSTM, one layer, RCU_F32, no lengths.
+ * (it may synchronise the device or fail under memory pressure).  The
+ * recurrent-cell unroll method this library implements has no counterpart
+ * to this entry point: it is an addition for such callers, and computes the
+ * same LSTM as rnn_forward with cell RCU_LSTM, one layer, RCU_F32, no lengths.
  *
  *   x [T, B, in_dim]; W_ih [4H, in_dim]; W_hh [4H, H]; b_ih, b_hh [4H] or
  *   NULL (zero); h0, c0 [B, H] or NULL (zero): device, fp32, PyTorch layout.
@@ -323,9 +324,11 @@ RCU_API int rnn_destroy(rcu_rnn_t h);
  * any work is enqueued.  All calls share the array and each overwrites it:
  * calls that overlap on the GPU (e.g. on two streams) race.  The first call
  * on a device looks up the array's device address with that device current
- * and caches it; make that first call before any stream capture.  The call
- * is synchronous: it returns after the work on `stream` has finished,
- * with RCU_ERR_TIMEOUT if a device step barrier gave up.
+ * and caches it.  The call is synchronous (it waits for `stream` and reads
+ * the device status back), so it cannot be used while `stream` is being
+ * captured into a CUDA graph.  It returns after the work on `stream` has
+ * finished: RCU_ERR_TIMEOUT if a device step barrier gave up, RCU_ERR_CUDA for
+ * any other launch or device error.
  */
 RCU_API int rnn_lstm_forward_noalloc(int T, int B, int in_dim, int hidden, const float *x,
                                      const float *W_ih, const float *W_hh, const float *b_ih,

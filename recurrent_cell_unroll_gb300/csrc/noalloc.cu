@@ -187,8 +187,17 @@ extern "C" int rnn_lstm_forward_noalloc(int T, int B, int in_dim, int hidden, co
   const int R = 4 * p.U;
   p.CB = B < 32 ? B : 32;
   auto smem_of = [&](int cb) { return ((size_t)H * R + (size_t)H * cb + (size_t)cb * R) * 4; };
-  while (p.CB > 1 && smem_of(p.CB) > 227 * 1024) --p.CB;
-  if (smem_of(p.CB) > 227 * 1024)
+  // dynamic shared memory may use what the device allows a block by opt-in,
+  // less the kernel's own static shared memory (the step barrier's flag)
+  int optin = 0;
+  cudaFuncAttributes fa{};
+  if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+          cudaSuccess ||
+      (e = cudaFuncGetAttributes(&fa, (const void *)lstm_noalloc_kernel)) != cudaSuccess)
+    return set_error(RCU_ERR_CUDA, cudaGetErrorString(e));
+  const size_t smem_cap = (size_t)optin > fa.sharedSizeBytes ? (size_t)optin - fa.sharedSizeBytes : 0;
+  while (p.CB > 1 && smem_of(p.CB) > smem_cap) --p.CB;
+  if (smem_of(p.CB) > smem_cap)
     return set_error(RCU_ERR_UNSUPPORTED, "rnn_lstm_forward_noalloc: hidden too large");
   p.G = G; p.W_hh = W_hh; p.h0 = h0; p.c0 = c0; p.y = y; p.h_n = h_n; p.c_n = c_n;
   p.hx = hx; p.hst = hst; p.cst = cst;
@@ -200,6 +209,8 @@ extern "C" int rnn_lstm_forward_noalloc(int T, int B, int in_dim, int hidden, co
   if ((e = cudaMemsetAsync(ctl, 0, 256, s)) != cudaSuccess)
     return set_error(RCU_ERR_CUDA, cudaGetErrorString(e));
   bias_sum_kernel<<<(4 * H + 255) / 256, 256, 0, s>>>(b_ih, b_hh, bias, 4 * H);
+  if ((e = cudaGetLastError()) != cudaSuccess)
+    return set_error(RCU_ERR_CUDA, cudaGetErrorString(e));
   if ((e = launch_gemm_simt<float, float>(x, in_dim, W_ih, in_dim, bias, G, 4 * H, T * B,
                                            nullptr, 4 * H, in_dim, s, p.err)) != cudaSuccess)
     return set_error(RCU_ERR_CUDA, cudaGetErrorString(e));
@@ -218,7 +229,17 @@ extern "C" int rnn_lstm_forward_noalloc(int T, int B, int in_dim, int hidden, co
   int dstat = 0;
   if ((e = cudaMemcpy(&dstat, p.err, sizeof dstat, cudaMemcpyDeviceToHost)) != cudaSuccess)
     return set_error(RCU_ERR_CUDA, cudaGetErrorString(e));
-  if (dstat != DEV_OK)
-    return set_error(RCU_ERR_TIMEOUT, "rnn_lstm_forward_noalloc: a step barrier timed out");
-  return RCU_OK;
+  switch (dstat) {
+    case DEV_OK: return RCU_OK;
+    case DEV_TIMEOUT:
+      return set_error(RCU_ERR_TIMEOUT, "rnn_lstm_forward_noalloc: a step barrier timed out");
+    case DEV_CONFIG:
+      return set_error(RCU_ERR_CUDA,
+                       "rnn_lstm_forward_noalloc: a cluster kernel ran without its cluster shape");
+    default: {
+      char msg[96];
+      snprintf(msg, sizeof msg, "rnn_lstm_forward_noalloc: device error code %d", dstat);
+      return set_error(RCU_ERR_CUDA, msg);
+    }
+  }
 }
