@@ -449,9 +449,25 @@ TRAFFIC = {
 }
 
 
-def roofline(spec, inp, prof, peaks, nsm, step_ms=None):
+# A timed region shorter than this runs at the burst tensor rate (the
+# measured bf16 peak of a short GEMM); a longer one settles under the power
+# cap, where the sustained measurement applies.
+SUSTAINED_AFTER_S = 2.0
+
+
+def bf16_peak(peaks, region_s):
+    """(TFLOP/s, note) of the bf16 tensor peak that applies to a timed region."""
+    if region_s is not None and region_s >= SUSTAINED_AFTER_S:
+        return peaks["bf16_tflops_sustained"], \
+            f"bf16 dense, sustained ({peaks['source']}): timed region {region_s:.2f} s"
+    return peaks["bf16_tflops"], f"bf16 dense, burst ({peaks['source']}): timed region " + \
+        ("unknown" if region_s is None else f"{region_s:.2f} s") + \
+        f" < {SUSTAINED_AFTER_S:.0f} s"
+
+
+def roofline(spec, inp, prof, peaks, nsm, step_ms=None, region_s=None):
     """Roofline of the dominant kernel from the live event timings."""
-    r = _roofline(spec, inp, prof, peaks, nsm, step_ms)
+    r = _roofline(spec, inp, prof, peaks, nsm, step_ms, region_s)
     if r is not None:
         tr = TRAFFIC.get((spec.name, r["kernel"]))
         r["traffic"] = tr
@@ -460,7 +476,7 @@ def roofline(spec, inp, prof, peaks, nsm, step_ms=None):
     return r
 
 
-def _roofline(spec, inp, prof, peaks, nsm, step_ms=None):
+def _roofline(spec, inp, prof, peaks, nsm, step_ms=None, region_s=None):
     if isinstance(spec, wl.RssmSpec) and not spec.train:
         # one kernel per step: its launch time is the event-timed step
         per_launch = kernel_flops(spec, inp)["rssm"][0]
@@ -483,8 +499,8 @@ def _roofline(spec, inp, prof, peaks, nsm, step_ms=None):
     avg_s = ms / 1e3 / n
     achieved = per_launch / avg_s / 1e12
     if getattr(spec, "dtype", "f32") == "bf16":
-        peak, bound, note = peaks["bf16_tflops_sustained"], "tensor", \
-            f"bf16 dense, sustained, {peaks['source']}"
+        peak, note = bf16_peak(peaks, region_s)
+        bound = "tensor"
     else:
         peak, bound, note = fp32_alu_peak_tflops(nsm, peaks["sm_max_mhz"]), "alu", \
             "fp32 FFMA: SMs x 128 lanes x 2 x max SM clock"
@@ -553,33 +569,8 @@ def run_ours(args, spec, rank, local, ws):
     #      timed region alone)
     e2e = None
     if args.e2e_steps > 0:
-        host_in, host_out, host_call = e2e_io()
-        h2d = sum(v.numel() * v.element_size() for v in host_in)
-        d2h = sum(o.numel() * o.element_size() for o in host_out)
-        e2e_steps = max(1, min(args.steps, args.e2e_steps))
-        for it in range(e2e_steps + 1):
-            if it == 1:
-                dist_barrier()
-                torch.cuda.synchronize(dev)
-                ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                ea.record(stream)
-            host_call()
-        eb.record(stream)
-        torch.cuda.synchronize(dev)
-        e2e_ms = dist_max(ea.elapsed_time(eb) / e2e_steps, dev)
-        e2e_value = dist_sum(units(spec, inp), dev) / (e2e_ms / 1e3)
-        st = status()
-        if st != 0:
-            raise RuntimeError(f"device status {st} in the end-to-end loop")
-        e2e = {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-               "call": ("rssm_backward + rssm_get_weight_grads, pinned host copies on the stream"
-                        if getattr(spec, "train", False) else
-                        "rssm_unroll_actor_host" if getattr(spec, "actor_hidden", 0) else
-                        "rssm_unroll_host") if isinstance(spec, wl.RssmSpec) else
-               ("rnn_backward + rnn_get_weight_grads, pinned host copies on the stream"
-                if getattr(spec, "train", False) else "rnn_forward_host"),
-               "host_buffers": "pinned"}
+        e2e = run_e2e(args, spec, e2e_io, status, keep, dev, stream, local,
+                      max_ms / args.steps)
 
     peaks = load_peaks()
     extra = {}
@@ -595,8 +586,8 @@ def run_ours(args, spec, rank, local, ws):
         "dtype": "bf16" if getattr(spec, "dtype", "f32") == "bf16" else "f32",
         "data": "synthetic",
         "config": workload_config(spec, inp, ws),
-        "roofline": roofline(spec, inp, prof, peaks, nsm, dev_ms / args.steps),
-        "path_roofline": path_roofline(spec, inp, peaks, nsm, max_ms / args.steps),
+        "roofline": roofline(spec, inp, prof, peaks, nsm, dev_ms / args.steps, wall),
+        "path_roofline": path_roofline(spec, inp, peaks, nsm, max_ms / args.steps, wall),
         "kernels": {k: {"ms_total": round(v[0], 3), "launches": v[1]} for k, v in prof.items()}
         if prof else None,
         "e2e": e2e,
@@ -608,11 +599,129 @@ def run_ours(args, spec, rank, local, ws):
     return line, inp
 
 
-def path_roofline(spec, inp, peaks, nsm, ms_step):
+def gpu_cpu_affinity(index: int):
+    """CPUs nvidia-smi names as local to GPU `index` ("CPU Affinity" of
+    `nvidia-smi topo -m`), as a set, or None when it cannot be read."""
+    try:
+        out = subprocess.run(["nvidia-smi", "topo", "-m"], capture_output=True, text=True,
+                             timeout=20).stdout
+    except (OSError, subprocess.SubprocessError):
+        return None
+    cpus = parse_topo_affinity(out, index)
+    if cpus is None:
+        return None
+    return (cpus & os.sched_getaffinity(0)) or None
+
+
+def parse_topo_affinity(out: str, index: int):
+    """The "CPU Affinity" cell of GPU `index` in `nvidia-smi topo -m` output
+    (tab-separated; ranges like 0-71,144-215) as a set of CPUs, or None."""
+    lines = [ln for ln in out.splitlines() if ln.strip()]
+    if not lines:
+        return None
+    head = lines[0].split("\t")
+    col = next((i for i, h in enumerate(head) if "CPU Affinity" in h), None)
+    if col is None:
+        return None
+    for ln in lines[1:]:
+        f = ln.split("\t")
+        if f and f[0].strip() == f"GPU{index}" and len(f) > col:
+            cpus = set()
+            for part in f[col].strip().split(","):
+                if "-" in part:
+                    lo, hi = part.split("-")
+                    cpus.update(range(int(lo), int(hi) + 1))
+                elif part.strip().isdigit():
+                    cpus.add(int(part))
+            return cpus or None
+    return None
+
+
+def link_rates(host_in, host_out, dev, stream):
+    """GB/s of one host->device copy of the largest input and one device->host
+    copy of the largest output, each alone on the stream (after one untimed
+    copy of each), so the end-to-end figure can be read against the link."""
+    def timed(dst, src):
+        dst.copy_(src, non_blocking=True)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dst.copy_(src, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return src.numel() * src.element_size() / (a.elapsed_time(b) / 1e3) / 1e9
+    big_in = max(host_in, key=lambda t: t.numel() * t.element_size())
+    big_out = max(host_out, key=lambda t: t.numel() * t.element_size())
+    d_in = torch.empty(big_in.shape, dtype=big_in.dtype, device=dev)
+    d_out = torch.empty(big_out.shape, dtype=big_out.dtype, device=dev)
+    r = {"h2d_gbs": round(timed(d_in, big_in), 1), "d2h_gbs": round(timed(big_out, d_out), 1),
+         "h2d_probe_bytes": big_in.numel() * big_in.element_size(),
+         "d2h_probe_bytes": big_out.numel() * big_out.element_size()}
+    del d_in, d_out
+    return r
+
+
+def run_e2e(args, spec, e2e_io, status, keep, dev, stream, local, device_ms):
+    """The end-to-end leg: the public host-buffer call on pinned host buffers,
+    every step's inputs in and outputs out inside the timed region.  The
+    process runs on the GPU's local CPUs meanwhile (so the pinned buffers are
+    allocated on the GPU's NUMA node); the line records how the call moved
+    the data and the link's own rate for one copy each way."""
+    from recurrent_cell_unroll_gb300 import binding
+    old_aff = os.sched_getaffinity(0)
+    local_cpus = gpu_cpu_affinity(local)
+    if local_cpus:
+        os.sched_setaffinity(0, local_cpus)
+    try:
+        host_in, host_out, host_call = e2e_io()
+        h2d = sum(v.numel() * v.element_size() for v in host_in)
+        d2h = sum(o.numel() * o.element_size() for o in host_out)
+        e2e_steps = max(1, args.e2e_steps)
+        host_call()  # untimed: first touch of the staging buffers
+        dist_barrier()
+        torch.cuda.synchronize(dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(e2e_steps)]
+        for i in range(e2e_steps):
+            evs[i][0].record(stream)
+            host_call()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        per = [a.elapsed_time(b) for a, b in evs]
+        e2e_ms = dist_max(sum(per) / e2e_steps, dev)
+        e2e_value = dist_sum(units(spec, None), dev) / (e2e_ms / 1e3)
+        st = status()
+        if st != 0:
+            raise RuntimeError(f"device status {st} in the end-to-end loop")
+        link = link_rates(host_in, host_out, dev, stream)
+        plan = None
+        if isinstance(keep, binding.RNN) and not getattr(spec, "train", False):
+            plan = binding.rnn_host_plan(keep.h)
+    finally:
+        os.sched_setaffinity(0, old_aff)
+    return {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+            "ms_per_step_each": [round(x, 3) for x in per], "steps": e2e_steps,
+            "device_ms_per_step": round(device_ms, 4),
+            "link": link,
+            "h2d_ms_alone": round(h2d / (link["h2d_gbs"] * 1e9) * 1e3, 3),
+            "d2h_ms_alone": round(d2h / (link["d2h_gbs"] * 1e9) * 1e3, 3),
+            "host_plan": plan,
+            "cpu_affinity": (f"{min(local_cpus)}-{max(local_cpus)} ({len(local_cpus)} CPUs, "
+                             "local to the GPU)") if local_cpus else "unchanged",
+            "call": ("rssm_backward + rssm_get_weight_grads, pinned host copies on the stream"
+                     if getattr(spec, "train", False) else
+                     "rssm_unroll_actor_host" if getattr(spec, "actor_hidden", 0) else
+                     "rssm_unroll_host") if isinstance(spec, wl.RssmSpec) else
+            ("rnn_backward + rnn_get_weight_grads, pinned host copies on the stream"
+             if getattr(spec, "train", False) else "rnn_forward_host"),
+            "host_buffers": "pinned"}
+
+
+def path_roofline(spec, inp, peaks, nsm, ms_step, region_s=None):
     """Whole-step roofline: max(FLOPs / peak(dtype), compulsory bytes / HBM)."""
     fl = total_flops(spec, inp)
     if getattr(spec, "dtype", "f32") == "bf16":
-        peak = peaks["bf16_tflops_sustained"] * 1e12
+        peak = bf16_peak(peaks, region_s)[0] * 1e12
     else:
         peak = fp32_alu_peak_tflops(nsm, peaks["sm_max_mhz"]) * 1e12
     t_flop = fl / peak
@@ -782,6 +891,47 @@ def run_reference(args, spec):
     }
 
 
+# ----------------------------------------------------------------------------- the other configs
+
+# The shapes the metric is also quoted on, measured after the headline
+# workload in the same run (1 GPU only): the TVM page's LSTM, the RSSM prior,
+# the 2-layer LSTMP, the variable-length bidirectional LSTM, and the RSSM with
+# the actor in the loop.
+CONFIG_WORKLOADS = ("lstm", "rssm", "lstmp", "bilstm", "rssm_actor")
+
+
+def run_configs(args, rank, local, ws):
+    """One compact entry per config: throughput, per-step latency, the
+    dominant kernel's and the whole path's roofline fractions, the
+    end-to-end rate and a bounded CPU-oracle sample."""
+    out = {}
+    for name in CONFIG_WORKLOADS:
+        spec = WORKLOADS[name]
+        sub = argparse.Namespace(**vars(args))
+        sub.steps = max(3, min(args.steps, 10))
+        sub.e2e_steps = min(args.e2e_steps, 3)
+        line, inp = run_ours(sub, spec, rank, local, ws)
+        rf, pr, e2e = line["roofline"] or {}, line["path_roofline"] or {}, line["e2e"] or {}
+        entry = {
+            "value": line["value"], "unit": UNIT, "dtype": line["dtype"], "steps": sub.steps,
+            "ms_per_step": line["ms_per_step"], "us_per_timestep": line["us_per_timestep"],
+            "roofline": {k: rf.get(k) for k in ("kernel", "bound", "achieved", "peak", "unit",
+                                                "frac", "avg_launch_ms", "traffic")},
+            "path_roofline": {k: pr.get(k) for k in ("roofline_ms", "frac")},
+            "e2e": {k: e2e.get(k) for k in ("value", "ms_per_step", "host_plan")} if e2e
+            else None,
+            "clocks": line["clocks"],
+        }
+        if "tokens_per_s" in line:
+            entry["tokens_per_s"] = line["tokens_per_s"]
+        if not args.no_cpu_baseline:
+            entry["cpu_baseline"] = cpu_baseline(spec, inp, args.config_cpu_budget)
+        out[spec.name] = entry
+        del line, inp
+        torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------------------------- main
 
 def main(argv=None):
@@ -792,10 +942,14 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gru", choices=sorted(WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--e2e-steps", type=int, default=3,
+    ap.add_argument("--e2e-steps", type=int, default=5,
                     help="steps of the host-buffer end-to-end leg (0 = skip it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other configs measured after the default workload")
+    ap.add_argument("--config-cpu-budget", type=float, default=6.0,
+                    help="seconds of CPU-oracle work per extra config")
     ap.add_argument("--T", type=int, default=0,
                     help="override the sequence length (small cases for profiler captures)")
     ap.add_argument("--dtype", default="", choices=["", "f32", "bf16"],
@@ -828,6 +982,9 @@ def main(argv=None):
             line["cpu_baseline"] = cpu_baseline(spec, inp, args.cpu_budget)
         else:
             line["cpu_baseline"] = None
+        if (ws == 1 and not args.no_configs and args.workload == "gru" and args.T == 0 and
+                not args.dtype and not args.tc_ksplit):
+            line["configs"] = run_configs(args, rank, local, ws)
         print(json.dumps(line), flush=True)
     if torch.distributed.is_initialized():
         torch.distributed.destroy_process_group()

@@ -194,6 +194,16 @@ RCU_API int rnn_forward_host(rcu_rnn_t h, int T, int B, const float *x, const in
                              void *stream);
 
 /*
+ * How the last rnn_forward_host call on `h` moved x and y (host pointers to
+ * ints, each may be NULL): *chunks = steps chunks of the pipelined form (1 =
+ * one forward over all steps); *x_in_place / *y_in_place = 1 when the kernels
+ * read x / wrote y through the page-locked host buffer's device address, 0
+ * when the data went through device staging buffers and the copy engines.
+ * All 0 before the first call.  A description only: no device work.
+ */
+RCU_API int rnn_host_plan(rcu_rnn_t h, int *chunks, int *x_in_place, int *y_in_place);
+
+/*
  * Backward pass through time (BPTT), the training use of the unrolled cell
  * ("[Feature Request] CUDNN version of RSSM", pytorch/rl issue 366,
  * Motivation; "Integrating CuDNN API for LSTMs with projections",

@@ -41,7 +41,7 @@ EXPORTED = (
     "rssm_set_actor", "rssm_unroll_actor", "rnn_forward_host", "rssm_unroll_host",
     "rssm_unroll_actor_host", "rnn_backward", "rnn_get_weight_grads", "rssm_backward",
     "rssm_get_weight_grads", "rssm_profile_entry", "rssm_profile_reset", "rssm_backward_actor",
-    "rssm_get_actor_grads",
+    "rssm_get_actor_grads", "rnn_host_plan",
 )
 
 _lib = None
@@ -72,6 +72,7 @@ def signatures() -> dict:
         "rnn_set_attr": (I, [P, I, I64]),
         "rnn_set_clip": (I, [P, I, I, ctypes.c_double, ctypes.c_double]),
         "rnn_last_launch_count": (I, [P]),
+        "rnn_host_plan": (I, [P, ctypes.POINTER(I), ctypes.POINTER(I), ctypes.POINTER(I)]),
         "rnn_destroy": (I, [P]),
         "rnn_profile_entry": (I, [P, I, ctypes.POINTER(ctypes.c_char_p),
                                   ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I64)]),
@@ -285,6 +286,13 @@ def rnn_forward_host(h, T: int, B: int, x, lengths, h0, c0, y, h_n, c_n, stream=
     outs = [_host(t, out=True) for t in (y, h_n, c_n)]
     _check(load().rnn_forward_host(h, T, B, *[k[1] for k in ins], *[k[1] for k in outs],
                                    _stream(stream)))
+
+
+def rnn_host_plan(h) -> dict:
+    """How the last rnn_forward_host call moved x and y (see rcu.h)."""
+    c, xi, yi = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    _check(load().rnn_host_plan(h, ctypes.byref(c), ctypes.byref(xi), ctypes.byref(yi)))
+    return {"chunks": c.value, "x_in_place": bool(xi.value), "y_in_place": bool(yi.value)}
 
 
 def rnn_backward(h, T: int, B: int, x, lengths, h0, c0, dy, dh_n, dc_n, dx, dh0, dc0,

@@ -88,6 +88,8 @@ struct rcu_rnn_s : EventProfiler {
   // (then always through the packing kernel's plain loads)
   DevBuf io_x, io_len, io_h0, io_c0, io_y, io_hn, io_cn;
   bool x_in_place = false;
+  // what the last rnn_forward_host did (rnn_host_plan)
+  int plan_chunks = 0, plan_x_in_place = 0, plan_y_in_place = 0;
   // rnn_forward_host over chunks of steps: two copy streams, double-buffered
   // x / y chunks, ping-pong per-layer state, events
   int host_chunks = 0;  // RCU_ATTR_HOST_CHUNKS
@@ -825,8 +827,11 @@ extern "C" int rnn_forward_host(rcu_rnn_t h, int T, int B, const float *x, const
   int n = h->host_chunks;
   if (n == 0) n = x_bytes + y_bytes >= ((size_t)64 << 20) ? std::min(8, T / 64) : 1;
   n = std::min(n, T);
-  if (n > 1 && h->D == 1 && h->P == 0 && !lengths && device_address(x) && device_address(y))
+  if (n > 1 && h->D == 1 && h->P == 0 && !lengths && device_address(x) && device_address(y)) {
+    h->plan_chunks = n;
+    h->plan_x_in_place = h->plan_y_in_place = 0;
     return forward_host_chunked(h, T, B, n, x, h0, c0, y, h_n, c_n, (cudaStream_t)stream);
+  }
 
   HostIO io{(cudaStream_t)stream, {}};
   const void *dx, *dlen, *dh0, *dc0;
@@ -841,6 +846,9 @@ extern "C" int rnn_forward_host(rcu_rnn_t h, int T, int B, const float *x, const
   CU(io.out(h_n, LDB * h->Hout * 4, h->io_hn, false, &dhn));
   CU(io.out(c_n, LDB * h->H * 4, h->io_cn, false, &dcn));
   h->x_in_place = x_placed;
+  h->plan_chunks = 1;
+  h->plan_x_in_place = x_placed ? 1 : 0;
+  h->plan_y_in_place = dy == device_address(y) ? 1 : 0;
   const int rc = rnn_forward(h, T, B, (const float *)dx, (const int32_t *)dlen,
                              (const float *)dh0, (const float *)dc0, nullptr, (float *)dy,
                              (float *)dhn, (float *)dcn, stream);
@@ -1169,6 +1177,14 @@ extern "C" int rnn_get_status(rcu_rnn_t h, void *stream) {
 }
 
 extern "C" int rnn_last_launch_count(rcu_rnn_t h) { return h ? h->launches : -1; }
+
+extern "C" int rnn_host_plan(rcu_rnn_t h, int *chunks, int *x_in_place, int *y_in_place) {
+  if (!h) return fail(RCU_ERR_INVALID, "rnn_host_plan: NULL handle");
+  if (chunks) *chunks = h->plan_chunks;
+  if (x_in_place) *x_in_place = h->plan_x_in_place;
+  if (y_in_place) *y_in_place = h->plan_y_in_place;
+  return RCU_OK;
+}
 
 extern "C" int rnn_profile_entry(rcu_rnn_t h, int i, const char **name, double *total_ms,
                                  int64_t *count) {

@@ -195,3 +195,25 @@ def test_host_chunk_boundaries_cover_every_step_once():
             steps = [b - a for a, b in zip(t, t[1:])]
             assert t[0] == 0 and t[-1] == T and min(steps) >= 1 and len(steps) <= 16
     assert _chunk_starts(512, 8) == [0, 19, 98, 177, 256, 335, 414, 493, 512]
+
+
+def test_topology_cpu_affinity_parsing():
+    """The GPU's local CPUs come from the "CPU Affinity" column of nvidia-smi's
+    topology matrix (tab-separated, ranges and lists)."""
+    import bench
+    text = ("\tGPU0\tGPU1\tCPU Affinity\tNUMA Affinity\tGPU NUMA ID\n"
+            "GPU0\t X \tNV18\t0-3,8\t0\t2\n"
+            "GPU1\tNV18\t X \t4-7\t1\t3\n\n"
+            "Legend:\n\n  X    = Self\n")
+    assert bench.parse_topo_affinity(text, 0) == {0, 1, 2, 3, 8}
+    assert bench.parse_topo_affinity(text, 1) == {4, 5, 6, 7}
+    assert bench.parse_topo_affinity(text, 2) is None
+    assert bench.parse_topo_affinity("no table here", 0) is None
+
+
+def test_bf16_peak_choice_follows_the_timed_region():
+    import bench
+    peaks = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "measured"}
+    assert bench.bf16_peak(peaks, 0.3)[0] == 1900.0
+    assert bench.bf16_peak(peaks, None)[0] == 1900.0
+    assert bench.bf16_peak(peaks, 5.0)[0] == 1700.0

@@ -316,16 +316,22 @@ def test_input_projection_k_split(in_dim):
 ], ids=lambda s: s.name)
 def test_opt_in_bf16_conversion_accuracy(spec):
     """An fp32 workload run through the opt-in down-conversion (a bf16 handle:
-    weights and MMA operands rounded to bf16, fp32 state and accumulation),
-    against the exact fp32 model (the oracle with unrounded weights)."""
+    weights and MMA operands rounded to bf16, fp32 state and accumulation).
+    Parity is asserted against the model the conversion defines (the oracle
+    with the same bf16-rounded weights) at the bf16 tolerance; the distance
+    from the exact fp32 model (the oracle with unrounded weights) includes
+    the weight quantisation, which no tolerance on the pages bounds, so it is
+    reported only."""
     inp = wl.make_rnn_inputs(spec, seed=29)
-    got = run_gpu(spec.scaled(dtype="bf16"), inp)
+    bspec = spec.scaled(dtype="bf16")
+    got = run_gpu(bspec, inp)
+    compare(bspec, got, run_oracle(bspec, inp))
     ref = oracle.rnn_forward(_cell(spec), inp["x"], inp["weights"], hidden=spec.hidden,
                              proj=spec.proj, bidirectional=spec.bidir, lengths=inp["lengths"],
                              h0=inp["h0"], c0=inp["c0"], bf16_weights=False)
     errs = {n: _rel(g, r) for n, g, r in zip(("y", "h_n", "c_n"), got, ref) if g is not None}
     print(f"{spec.name}: relative error of the bf16 conversion vs the fp32 model {errs}")
-    assert all(e <= 3e-2 for e in errs.values()), errs
+    assert all(np.isfinite(e) for e in errs.values()), errs
 
 
 CLIP = [
@@ -732,22 +738,61 @@ def test_forward_host_rejects_device_tensors():
 
 # ----------------------------------------------------------------------------- full-size workloads
 
+# Rows checked at full size (sorted order = original order without lengths).
+# GRU, B = 256: TMEM lanes 0, 31, 32, 63, 64, 95, 96, 127 of the first
+# 128-row batch group, the 127/128 group boundary and lanes of the second
+# group.  LSTMP, B = 32 (one group, 32 live lanes): 16 rows spread over it.
+# BiLSTM: every row whose length ties another's (the stable sort decides
+# their order), the longest and the shortest, and evenly spaced rows.
 FULL = [
-    (wl.LSTMP_2L, [0, 13, 31]),
-    (wl.BILSTM_VAR, None),       # rows chosen below: longest, shortest, a tie
-    (wl.GRU_3L, [0, 255]),
+    (wl.LSTMP_2L, [0, 1, 2, 5, 8, 11, 13, 15, 16, 19, 22, 24, 27, 29, 30, 31]),
+    (wl.BILSTM_VAR, None),
+    (wl.GRU_3L, [0, 1, 31, 32, 63, 64, 95, 96, 126, 127, 128, 129, 159, 191, 224, 255]),
 ]
+
+
+def full_size_rows(inp, B, n=16):
+    L = inp["lengths"].numpy()
+    vals, counts = np.unique(L, return_counts=True)
+    ties = [int(b) for b in range(B) if counts[np.searchsorted(vals, L[b])] > 1]
+    rows = set(ties) | {int(np.argmax(L)), int(np.argmin(L))}
+    for b in np.linspace(0, B - 1, n).astype(int):
+        if len(rows) >= max(n, len(ties) + 2):
+            break
+        rows.add(int(b))
+    return sorted(rows)
+
+
+def per_element_report(spec, got, ref, rows):
+    """Per-element error statistics of the sampled rows: the largest
+    |gpu - ref| / |ref| over elements with |ref| >= 10 % of their row's
+    max|ref|, and that row-normalised error's maximum (bf16)."""
+    out = {}
+    for name, g, r in (("y", got[0][:, rows], ref[0][:, rows]),):
+        big = np.abs(r) >= 0.1 * np.abs(r).max(axis=(0, 2), keepdims=True)
+        rel = np.abs(g - r)[big] / np.abs(r)[big]
+        rowmax = np.abs(r).max(axis=(0, 2), keepdims=True)
+        out[name] = {"max_rel_large_elems": float(rel.max()),
+                     "p999_rel_large_elems": float(np.quantile(rel, 0.999)),
+                     "max_row_normalised": float((np.abs(g - r) / np.maximum(rowmax, 1e-30)).max())}
+    return out
 
 
 @pytest.mark.parametrize("spec,rows", FULL, ids=lambda v: getattr(v, "name", "rows"))
 def test_full_size_sampled_rows(spec, rows):
     inp = wl.make_rnn_inputs(spec, seed=0)
     if rows is None:
-        L = inp["lengths"].numpy()
-        rows = [int(np.argmax(L)), int(np.argmin(L)), 17]
+        rows = full_size_rows(inp, spec.B)
+        assert len(rows) >= 16
     got = run_gpu(spec, inp)
     ref = run_oracle(spec, inp, rows=rows)
     compare(spec, got, ref, rows=rows)
+    if spec.dtype == "bf16":
+        # each sampled row against its own max|ref| (a bad row cannot hide
+        # behind a larger one); per-element statistics are printed
+        rep = per_element_report(spec, got, ref, rows)
+        print(f"\n{spec.name} per-element error over {len(rows)} rows: {rep}")
+        assert rep["y"]["max_row_normalised"] <= BF16_REL, rep
     if spec.varlen is not None:
         L = inp["lengths"].numpy()
         for b in range(spec.B):
