@@ -277,7 +277,7 @@ def make_rssm_train_runner(spec, inp, dev):
     return step, launches, profile_on, profile_read, e2e_io, status, m
 
 
-def make_runner(spec, inp, dev, tc_ksplit=0):
+def make_runner(spec, inp, dev, tc_ksplit=0, tc_options=0):
     from recurrent_cell_unroll_gb300 import binding
     if isinstance(spec, wl.RssmSpec) and spec.train:
         return make_rssm_train_runner(spec, inp, dev)
@@ -331,6 +331,8 @@ def make_runner(spec, inp, dev, tc_ksplit=0):
     net = binding.RNN.from_spec(spec)
     if tc_ksplit:
         net.set_attr(binding.RCU_ATTR_TC_KSPLIT, tc_ksplit)
+    if tc_options:
+        net.set_attr(binding.RCU_ATTR_TC_OPTIONS, tc_options)
     net.set_weights(inp["weights"], device=dev)
     d = {k: (None if inp[k] is None else inp[k].to(dev)) for k in ("x", "lengths", "h0", "c0")}
     T, B = spec.T, spec.B
@@ -522,7 +524,7 @@ def run_ours(args, spec, rank, local, ws):
     inp = (wl.make_rssm_inputs(spec, seed=args.seed + rank) if isinstance(spec, wl.RssmSpec)
            else wl.make_rnn_inputs(spec, seed=args.seed + rank))
     step, launches, profile_on, profile_read, e2e_io, status, keep = make_runner(
-        spec, inp, dev, args.tc_ksplit)
+        spec, inp, dev, args.tc_ksplit, args.tc_options)
     nsm = torch.cuda.get_device_properties(dev).multi_processor_count
     flush = torch.empty(int(2 * L2_BYTES // 4), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -957,6 +959,8 @@ def main(argv=None):
                          "opt-in down-conversion to the tensor cores)")
     ap.add_argument("--tc-ksplit", type=int, default=0, choices=[0, 1, 2, 4],
                     help="tensor-core recurrence: CTAs splitting K (0 = the library's choice)")
+    ap.add_argument("--tc-options", type=int, default=0,
+                    help="tensor-core recurrence: RCU_ATTR_TC_OPTIONS bits (0 = defaults)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -983,7 +987,7 @@ def main(argv=None):
         else:
             line["cpu_baseline"] = None
         if (ws == 1 and not args.no_configs and args.workload == "gru" and args.T == 0 and
-                not args.dtype and not args.tc_ksplit):
+                not args.dtype and not args.tc_ksplit and not args.tc_options):
             line["configs"] = run_configs(args, rank, local, ws)
         print(json.dumps(line), flush=True)
     if torch.distributed.is_initialized():

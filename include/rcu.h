@@ -79,13 +79,23 @@ typedef struct rcu_rssm_s *rcu_rssm_t;
                                          2 = tensor-core (tcgen05) kernels where supported,
                                          3 = cluster-resident recurrent kernel where W_hh
                                          fits one thread-block cluster (else SIMT) */
-#define RCU_ATTR_TRACE 5              /* 1 = record per-step timestamps (rnn_get_trace) */
+#define RCU_ATTR_TRACE 5              /* 1 = record per-step timestamps (rnn_get_trace);
+                                         2 = also every CTA's stamps of the tensor-core
+                                         recurrence for a window of steps */
 #define RCU_ATTR_TC_KSPLIT 7          /* tensor-core recurrent kernel: CTAs that split the
                                          K (= hidden) dimension of h W_hh^T, exchanging
                                          partial sums through distributed shared memory
                                          (0 = automatic: 2 where it fits, 1 = no split,
                                          2 = CTA pairs, 4 = clusters of 4; a split that
                                          does not fit falls back to the next smaller) */
+#define RCU_ATTR_TC_OPTIONS 9         /* tensor-core recurrent kernel: bitwise OR of
+                                         RCU_TC_OPT_* (0 = the defaults) */
+#define RCU_TC_OPT_TMA_PUBLISH 1      /* each CTA stages its h_t tile in shared memory and
+                                         publishes it with one TMA store (instead of
+                                         per-thread stores) */
+#define RCU_TC_OPT_SHARED_COUNTER_LINE 2 /* the step counters of all batch groups and
+                                         directions share one 128-byte line (by default
+                                         each has its own) */
 #define RCU_ATTR_PROFILE 4            /* 1 = record a CUDA event pair around every kernel
                                          this handle launches (RSSM handle: around each
                                          named phase of launches), on the launching
@@ -297,8 +307,11 @@ RCU_API int rnn_profile_reset(rcu_rnn_t h);
  * partial sums received (K split only), 6 gates done and h_t stored,
  * 7 epilogue threads joined, 4 h_t published; slots 9 and 10 hold the MMA
  * thread's clock cycles spent waiting for and issuing h stages.  Portable kernel
- * slots: 0 step start, 1 gates done, 2 barrier passed.  Synchronises the
- * stream.  host_out is host memory.
+ * slots: 0 step start, 1 gates done, 2 barrier passed.  With RCU_ATTR_TRACE
+ * = 2 the tensor-core kernel also stamps every CTA for steps 16 .. 23: row
+ * T + i*1024 + c holds the stamps of CTA c at step 16 + i (same slots; rows
+ * of CTAs past the grid stay 0), so n_steps up to T + 8192 rows are
+ * returned.  Synchronises the stream.  host_out is host memory.
  */
 RCU_API int rnn_get_trace(rcu_rnn_t h, int64_t *host_out, int n_steps, void *stream);
 

@@ -15,6 +15,10 @@
 #include "tc.h"
 #include "api_host.h"
 
+static_assert(rcu::TC_OPT_TMA_PUBLISH == RCU_TC_OPT_TMA_PUBLISH &&
+                  rcu::TC_OPT_SHARED_LINE == RCU_TC_OPT_SHARED_COUNTER_LINE,
+              "tensor-core option bits");
+
 using namespace rcu;
 using namespace rcu_api;
 
@@ -78,7 +82,8 @@ struct rcu_rnn_s : EventProfiler {
   int64_t timeout_ns = 2000000000LL;
   int drop_arrival = 0;
   int force_path = 0;
-  int tc_ksplit = 0;   // CTAs splitting K in the tensor-core recurrent kernel (0 = automatic)
+  int tc_ksplit = 0;
+  int tc_options = 0;  // RCU_ATTR_TC_OPTIONS   // CTAs splitting K in the tensor-core recurrent kernel (0 = automatic)
   // LSTM clipping (rnn_set_clip)
   int cclip = 0, pclip = 0;
   float cclip_lo = 0.f, cclip_hi = 0.f, pclip_lo = 0.f, pclip_hi = 0.f;
@@ -103,7 +108,7 @@ struct rcu_rnn_s : EventProfiler {
   bool grads_ready = false;
   float *keep_out = nullptr;
   // opt-in per-step trace of the first layer's recurrent kernel
-  bool trace = false;
+  int trace = 0;  // RCU_ATTR_TRACE: 1 = CTA 0 every step, 2 = also every CTA for a window
   DevBuf trace_buf;
   int trace_T = 0;
   void begin(const char *name, cudaStream_t s) { prof_begin(name, s); }
@@ -234,7 +239,13 @@ extern "C" int rnn_set_attr(rcu_rnn_t h, int attr, int64_t value) {
       h->tc_ksplit = (int)value;
       return RCU_OK;
     case RCU_ATTR_TRACE:
-      h->trace = value != 0;
+      if (value < 0 || value > 2) return fail(RCU_ERR_INVALID, "trace must be 0, 1 or 2");
+      h->trace = (int)value;
+      return RCU_OK;
+    case RCU_ATTR_TC_OPTIONS:
+      if (value < 0 || value > (RCU_TC_OPT_TMA_PUBLISH | RCU_TC_OPT_SHARED_COUNTER_LINE))
+        return fail(RCU_ERR_INVALID, "unknown tensor-core options %lld", (long long)value);
+      h->tc_options = (int)value;
       return RCU_OK;
     case RCU_ATTR_FORCE_PATH:
       if (value < 0 || value > 3) return fail(RCU_ERR_INVALID, "force_path must be 0, 1, 2 or 3");
@@ -494,9 +505,10 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
   CU(cudaMemsetAsync(h->ctl.p, 0, std::max(cbytes, ctl_bytes(h->layers)), s));
   CU(cudaMemsetAsync(h->hx, 0, (size_t)D * 2 * B * h->Kp * es, s));
   if (h->trace) {
-    CU(h->trace_buf.ensure((size_t)T * 16 * 8));
-    CU(cudaMemsetAsync(h->trace_buf.p, 0, (size_t)T * 16 * 8, s));
-    h->trace_T = T;
+    const size_t rows = (size_t)T + (h->trace == 2 ? (size_t)TRACE_ALL_N * TRACE_ALL_CTAS : 0);
+    CU(h->trace_buf.ensure(rows * 16 * 8));
+    CU(cudaMemsetAsync(h->trace_buf.p, 0, rows * 16 * 8, s));
+    h->trace_T = (int)rows;
   }
   if (h->P > 0) CU(cudaMemsetAsync(h->mx, 0, (size_t)D * B * h->Hp * es, s));
   if (varlen || T != h->meta_T || B != h->meta_B || s != h->meta_s) {
@@ -584,6 +596,8 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
     p.timeout_ns = (uint64_t)h->timeout_ns;
     p.drop_arrival = h->drop_arrival == 1 && l == 0;
     p.trace = (h->trace && l == 0) ? (unsigned long long *)h->trace_buf.p : nullptr;
+    p.trace_all = (h->trace == 2 && l == 0) ? (unsigned long long *)h->trace_buf.p + (size_t)T * 16
+                                            : nullptr;
     p.cclip = h->cclip;
     p.cclip_lo = h->cclip_lo;
     p.cclip_hi = h->cclip_hi;
@@ -621,6 +635,7 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
       TcRecParams tp;
       tp.base = pf;
       tp.ksplit = h->tc_ksplit;
+      tp.options = h->tc_options;
       for (int d = 0; d < D; ++d) tp.Wtc[d] = h->lw[(size_t)l * D + d].fold_w.p;
       h->begin("recurrent_tc_lstmp", s);
       cudaError_t e = launch_tc_recurrent(tp, h->nsm, s);
@@ -672,6 +687,7 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
       TcRecParams tp;
       tp.base = p;
       tp.ksplit = h->tc_ksplit;
+      tp.options = h->tc_options;
       for (int d = 0; d < D; ++d) tp.Wtc[d] = h->lw[(size_t)l * D + d].tc_whh.p;
       cudaError_t e = launch_tc_recurrent(tp, h->nsm, s);
       if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "tc recurrent: %s", cudaGetErrorString(e));

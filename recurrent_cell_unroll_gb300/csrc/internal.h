@@ -47,6 +47,8 @@ cudaError_t launch_gemm_simt(const XT *X, int ldx, const WT *W, int ldw, const f
                              cudaStream_t s, int *err);
 
 // ---- recurrent_simt.cu -------------------------------------------------------
+// all-CTA step trace window (RCU_ATTR_TRACE = 2)
+constexpr int TRACE_ALL_S0 = 16, TRACE_ALL_N = 8, TRACE_ALL_CTAS = 1024;
 struct RecParams {
   int T, B, H, Hout, Kp, Hp, nG, D, cell, proj;
   int U, NU, Rp;   // units per CTA, unit groups per direction, padded gate rows per CTA
@@ -69,7 +71,10 @@ struct RecParams {
   int *err;
   uint64_t timeout_ns;
   int drop_arrival;
-  unsigned long long *trace;  // NULL, or [T][8] global-timer stamps written by CTA 0
+  unsigned long long *trace;  // NULL, or [T][16] global-timer stamps written by CTA 0
+  // NULL, or stamps of every CTA for steps [TRACE_ALL_S0, TRACE_ALL_S0 + TRACE_ALL_N):
+  // row (step - TRACE_ALL_S0) * TRACE_ALL_CTAS + blockIdx.x, 16 slots (tensor-core kernel)
+  unsigned long long *trace_all;
   // LSTM clipping: c_t clamped to [cclip_lo, cclip_hi] when updated (cclip != 0);
   // projected h_t clamped to [pclip_lo, pclip_hi] when formed (pclip != 0)
   int cclip, pclip;

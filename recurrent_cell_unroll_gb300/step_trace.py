@@ -5,6 +5,11 @@ Runs one workload a few times, then once with the library's step trace on
 CTA 0, resolution about 256 ns) and prints the median time between stamps.
 
     python -m recurrent_cell_unroll_gb300.step_trace --workload gru --T 64 [--ksplit 1]
+        [--options N] [--all-ctas]
+
+--all-ctas (tensor-core recurrence): every CTA's stamps for steps 16..23, to
+see how far apart the CTAs publish h_t and how long the last publication
+takes to reach the other CTAs.
 
 Which stamps exist depends on the kernel that ran (named by the profile):
 tensor-core recurrence, portable SIMT recurrence, cluster-resident
@@ -49,7 +54,44 @@ def _medians(tr, phases):
     return out
 
 
-def run(workload: str, T: int = 0, ksplit: int = 0, seed: int = 0):
+ALL_S0, ALL_N, ALL_CTAS = 16, 8, 1024  # the library's all-CTA trace window
+
+
+def all_cta_summary(rows: np.ndarray):
+    """rows [ALL_N, ALL_CTAS, 16] of stamps.  Per step t (of the window):
+    spread of the CTAs' publication times (slot 4), and the time from the
+    last publication of step t to the first / median / last CTA seeing
+    step t+1's barrier (slot 0)."""
+    live = np.any(rows[0] != 0, axis=1)
+    R = rows[:, live, :].astype(np.float64)
+    out = {"ctas": int(live.sum())}
+    spread, first, med, last, land, mma = [], [], [], [], [], []
+    for i in range(ALL_N - 1):
+        pub, nxt = R[i, :, 4], R[i + 1, :, 0]
+        if not (np.all(pub) and np.all(nxt)):
+            continue
+        spread.append(pub.max() - pub.min())
+        first.append(nxt.min() - pub.max())
+        med.append(np.median(nxt) - pub.max())
+        last.append(nxt.max() - pub.max())
+        land.append(np.median(R[i + 1, :, 1] - R[i + 1, :, 0]))
+        mma.append(np.median(R[i + 1, :, 2] - R[i + 1, :, 1]))
+    if spread:
+        out.update({
+            "publish_spread_ns": float(np.median(spread)),
+            "last_publish_to_first_barrier_seen_ns": float(np.median(first)),
+            "last_publish_to_median_barrier_seen_ns": float(np.median(med)),
+            "last_publish_to_last_barrier_seen_ns": float(np.median(last)),
+            "median_barrier_seen_to_first_stage_ns": float(np.median(land)),
+            "median_first_stage_to_last_mma_ns": float(np.median(mma))})
+        # which CTAs publish last, most often
+        lastc = [int(np.argmax(R[i, :, 4])) for i in range(ALL_N) if np.all(R[i, :, 4])]
+        out["last_publisher_ctas"] = lastc
+    return out
+
+
+def run(workload: str, T: int = 0, ksplit: int = 0, seed: int = 0, options: int = 0,
+        all_ctas: bool = False):
     spec = WORKLOADS[workload]
     if T > 0:
         kw = {"T": T}
@@ -79,6 +121,8 @@ def run(workload: str, T: int = 0, ksplit: int = 0, seed: int = 0):
         net = binding.RNN.from_spec(spec)
         if ksplit:
             net.set_attr(binding.RCU_ATTR_TC_KSPLIT, ksplit)
+        if options:
+            net.set_attr(binding.RCU_ATTR_TC_OPTIONS, options)
         net.set_weights(inp["weights"])
         x = inp["x"].to(dev)
         h0 = inp["h0"].to(dev) if inp["h0"] is not None else None
@@ -86,7 +130,7 @@ def run(workload: str, T: int = 0, ksplit: int = 0, seed: int = 0):
         L = inp["lengths"].to(dev) if inp["lengths"] is not None else None
         for _ in range(3):
             net.forward(x, lengths=L, h0=h0, c0=c0)
-        net.set_attr(binding.RCU_ATTR_TRACE, 1)
+        net.set_attr(binding.RCU_ATTR_TRACE, 2 if all_ctas else 1)
         net.set_attr(binding.RCU_ATTR_PROFILE, 1)
         net.forward(x, lengths=L, h0=h0, c0=c0)
         torch.cuda.synchronize()
@@ -95,12 +139,17 @@ def run(workload: str, T: int = 0, ksplit: int = 0, seed: int = 0):
         names = net.profile()
         kernel = next((k for k in ("recurrent_tc", "recurrent_cluster", "recurrent_simt")
                        if any(n.startswith(k) for n in names)), "recurrent_simt")
-        tr = binding.rnn_get_trace(net.h, spec.T).numpy().astype(np.float64)
+        rows = spec.T + (ALL_N * ALL_CTAS if all_ctas else 0)
+        full = binding.rnn_get_trace(net.h, rows).numpy()
+        tr = full[:spec.T].astype(np.float64)
+        allc = full[spec.T:].reshape(ALL_N, ALL_CTAS, 16) if all_ctas else None
         net.close()
     body = tr[2:max(3, spec.T - 1)]  # skip the first steps (cold) and the last
     period = float(np.median(np.diff(body[:, 0]))) if len(body) > 1 else float("nan")
     res = {"workload": spec.name, "T": spec.T, "kernel": kernel, "step_period_ns": period,
            "phases_ns": _medians(body, PHASES[kernel])}
+    if not isinstance(spec, wl.RssmSpec) and all_ctas:
+        res["all_ctas"] = all_cta_summary(allc)
     if kernel == "recurrent_tc" and np.any(body[:, 10]):
         res["mma_thread_cycles"] = {"issuing": float(np.median(body[:, 10])),
                                     "waiting": float(np.median(body[:, 9]))}
@@ -113,8 +162,11 @@ def main(argv=None):
     ap.add_argument("--workload", default="gru", choices=sorted(WORKLOADS))
     ap.add_argument("--T", type=int, default=64, help="sequence length (0 = the workload's)")
     ap.add_argument("--ksplit", type=int, default=0, choices=[0, 1, 2, 4])
+    ap.add_argument("--options", type=int, default=0, help="RCU_ATTR_TC_OPTIONS bits")
+    ap.add_argument("--all-ctas", action="store_true",
+                    help="also every CTA's stamps for steps 16..23 (tensor-core kernel)")
     args = ap.parse_args(argv)
-    r = run(args.workload, args.T, args.ksplit)
+    r = run(args.workload, args.T, args.ksplit, options=args.options, all_ctas=args.all_ctas)
     print(f"{r['workload']} T={r['T']} kernel={r['kernel']} "
           f"step period (median) {r['step_period_ns']:.0f} ns")
     for label, v in r["phases_ns"]:
@@ -123,6 +175,9 @@ def main(argv=None):
         c = r["mma_thread_cycles"]
         print(f"  MMA thread clock cycles: issuing {c['issuing']:.0f}, waiting {c['waiting']:.0f}")
         print(f"  {'h_t published -> next step barrier seen':45s} {r['barrier_ns']:8.0f} ns")
+    if "all_ctas" in r:
+        for k, v in r["all_ctas"].items():
+            print(f"  all CTAs: {k:45s} {v}")
     return 0
 
 
