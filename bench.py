@@ -277,7 +277,7 @@ def make_rssm_train_runner(spec, inp, dev):
     return step, launches, profile_on, profile_read, e2e_io, status, m
 
 
-def make_runner(spec, inp, dev, tc_ksplit=0, tc_options=0):
+def make_runner(spec, inp, dev, tc_ksplit=0, tc_replicas=0):
     from recurrent_cell_unroll_gb300 import binding
     if isinstance(spec, wl.RssmSpec) and spec.train:
         return make_rssm_train_runner(spec, inp, dev)
@@ -331,8 +331,8 @@ def make_runner(spec, inp, dev, tc_ksplit=0, tc_options=0):
     net = binding.RNN.from_spec(spec)
     if tc_ksplit:
         net.set_attr(binding.RCU_ATTR_TC_KSPLIT, tc_ksplit)
-    if tc_options:
-        net.set_attr(binding.RCU_ATTR_TC_OPTIONS, tc_options)
+    if tc_replicas:
+        net.set_attr(binding.RCU_ATTR_TC_COUNTER_REPLICAS, tc_replicas)
     net.set_weights(inp["weights"], device=dev)
     d = {k: (None if inp[k] is None else inp[k].to(dev)) for k in ("x", "lengths", "h0", "c0")}
     T, B = spec.T, spec.B
@@ -467,9 +467,9 @@ def bf16_peak(peaks, region_s):
         f" < {SUSTAINED_AFTER_S:.0f} s"
 
 
-def roofline(spec, inp, prof, peaks, nsm, step_ms=None, region_s=None):
+def roofline(spec, inp, prof, peaks, nsm, step_ms=None, region_s=None, steps=1):
     """Roofline of the dominant kernel from the live event timings."""
-    r = _roofline(spec, inp, prof, peaks, nsm, step_ms, region_s)
+    r = _roofline(spec, inp, prof, peaks, nsm, step_ms, region_s, steps)
     if r is not None:
         tr = TRAFFIC.get((spec.name, r["kernel"]))
         r["traffic"] = tr
@@ -478,7 +478,7 @@ def roofline(spec, inp, prof, peaks, nsm, step_ms=None, region_s=None):
     return r
 
 
-def _roofline(spec, inp, prof, peaks, nsm, step_ms=None, region_s=None):
+def _roofline(spec, inp, prof, peaks, nsm, step_ms=None, region_s=None, steps=1):
     if isinstance(spec, wl.RssmSpec) and not spec.train:
         # one kernel per step: its launch time is the event-timed step
         per_launch = kernel_flops(spec, inp)["rssm"][0]
@@ -497,7 +497,9 @@ def _roofline(spec, inp, prof, peaks, nsm, step_ms=None, region_s=None):
         "input_gemm" if name.startswith("input_gemm") else None)
     if kind is None:
         return None
-    per_launch = sum(fl[kind]) / len(fl[kind])
+    # the kind's FLOPs of all timed steps over its launches (one launch per
+    # layer, or one per chunk of steps when the layers are pipelined)
+    per_launch = sum(fl[kind]) * steps / n
     avg_s = ms / 1e3 / n
     achieved = per_launch / avg_s / 1e12
     if getattr(spec, "dtype", "f32") == "bf16":
@@ -524,7 +526,7 @@ def run_ours(args, spec, rank, local, ws):
     inp = (wl.make_rssm_inputs(spec, seed=args.seed + rank) if isinstance(spec, wl.RssmSpec)
            else wl.make_rnn_inputs(spec, seed=args.seed + rank))
     step, launches, profile_on, profile_read, e2e_io, status, keep = make_runner(
-        spec, inp, dev, args.tc_ksplit, args.tc_options)
+        spec, inp, dev, args.tc_ksplit, args.tc_replicas)
     nsm = torch.cuda.get_device_properties(dev).multi_processor_count
     flush = torch.empty(int(2 * L2_BYTES // 4), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -588,7 +590,7 @@ def run_ours(args, spec, rank, local, ws):
         "dtype": "bf16" if getattr(spec, "dtype", "f32") == "bf16" else "f32",
         "data": "synthetic",
         "config": workload_config(spec, inp, ws),
-        "roofline": roofline(spec, inp, prof, peaks, nsm, dev_ms / args.steps, wall),
+        "roofline": roofline(spec, inp, prof, peaks, nsm, dev_ms / args.steps, wall, args.steps),
         "path_roofline": path_roofline(spec, inp, peaks, nsm, max_ms / args.steps, wall),
         "kernels": {k: {"ms_total": round(v[0], 3), "launches": v[1]} for k, v in prof.items()}
         if prof else None,
@@ -678,7 +680,10 @@ def run_e2e(args, spec, e2e_io, status, keep, dev, stream, local, device_ms):
         h2d = sum(v.numel() * v.element_size() for v in host_in)
         d2h = sum(o.numel() * o.element_size() for o in host_out)
         e2e_steps = max(1, args.e2e_steps)
-        host_call()  # untimed: first touch of the staging buffers
+        # untimed warm-up calls: the first calls after the staging buffers and
+        # copy streams are set up run slower (one measured 3x the steady step)
+        for _ in range(max(3, args.warmup)):
+            host_call()
         dist_barrier()
         torch.cuda.synchronize(dev)
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -959,8 +964,8 @@ def main(argv=None):
                          "opt-in down-conversion to the tensor cores)")
     ap.add_argument("--tc-ksplit", type=int, default=0, choices=[0, 1, 2, 4],
                     help="tensor-core recurrence: CTAs splitting K (0 = the library's choice)")
-    ap.add_argument("--tc-options", type=int, default=0,
-                    help="tensor-core recurrence: RCU_ATTR_TC_OPTIONS bits (0 = defaults)")
+    ap.add_argument("--tc-replicas", type=int, default=0,
+                    help="tensor-core recurrence: step-counter replicas (0 = the library's)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -987,7 +992,7 @@ def main(argv=None):
         else:
             line["cpu_baseline"] = None
         if (ws == 1 and not args.no_configs and args.workload == "gru" and args.T == 0 and
-                not args.dtype and not args.tc_ksplit and not args.tc_options):
+                not args.dtype and not args.tc_ksplit and not args.tc_replicas):
             line["configs"] = run_configs(args, rank, local, ws)
         print(json.dumps(line), flush=True)
     if torch.distributed.is_initialized():

@@ -88,14 +88,16 @@ typedef struct rcu_rssm_s *rcu_rssm_t;
                                          (0 = automatic: 2 where it fits, 1 = no split,
                                          2 = CTA pairs, 4 = clusters of 4; a split that
                                          does not fit falls back to the next smaller) */
-#define RCU_ATTR_TC_OPTIONS 9         /* tensor-core recurrent kernel: bitwise OR of
-                                         RCU_TC_OPT_* (0 = the defaults) */
-#define RCU_TC_OPT_TMA_PUBLISH 1      /* each CTA stages its h_t tile in shared memory and
-                                         publishes it with one TMA store (instead of
-                                         per-thread stores) */
-#define RCU_TC_OPT_SHARED_COUNTER_LINE 2 /* the step counters of all batch groups and
-                                         directions share one 128-byte line (by default
-                                         each has its own) */
+#define RCU_ATTR_LAYER_PIPELINE 10    /* 1 (default) = a stacked unidirectional bf16 LSTMP
+                                         whose tensor-core recurrence leaves room for a second
+                                         one runs its layers concurrently over chunks of
+                                         steps (layer l+1 on chunk c while layer l runs chunk
+                                         c+1), on streams the handle owns; results equal the
+                                         layer-by-layer ones.  0 = layer by layer */
+#define RCU_ATTR_TC_COUNTER_REPLICAS 9 /* tensor-core recurrent kernel: copies of each step
+                                         counter, each on its own 128-byte line; every CTA
+                                         adds to all of them and polls one (1 .. 16,
+                                         default 8) */
 #define RCU_ATTR_PROFILE 4            /* 1 = record a CUDA event pair around every kernel
                                          this handle launches (RSSM handle: around each
                                          named phase of launches), on the launching

@@ -15,9 +15,6 @@
 #include "tc.h"
 #include "api_host.h"
 
-static_assert(rcu::TC_OPT_TMA_PUBLISH == RCU_TC_OPT_TMA_PUBLISH &&
-                  rcu::TC_OPT_SHARED_LINE == RCU_TC_OPT_SHARED_COUNTER_LINE,
-              "tensor-core option bits");
 
 using namespace rcu;
 using namespace rcu_api;
@@ -82,8 +79,8 @@ struct rcu_rnn_s : EventProfiler {
   int64_t timeout_ns = 2000000000LL;
   int drop_arrival = 0;
   int force_path = 0;
-  int tc_ksplit = 0;
-  int tc_options = 0;  // RCU_ATTR_TC_OPTIONS   // CTAs splitting K in the tensor-core recurrent kernel (0 = automatic)
+  int tc_ksplit = 0;   // CTAs splitting K in the tensor-core recurrent kernel (0 = automatic)
+  int tc_replicas = 8;  // RCU_ATTR_TC_COUNTER_REPLICAS
   // LSTM clipping (rnn_set_clip)
   int cclip = 0, pclip = 0;
   float cclip_lo = 0.f, cclip_hi = 0.f, pclip_lo = 0.f, pclip_hi = 0.f;
@@ -101,6 +98,13 @@ struct rcu_rnn_s : EventProfiler {
   cudaStream_t cp_in = nullptr, cp_out = nullptr;
   std::vector<cudaEvent_t> chunk_ev;
   DevBuf io_xc[2], io_yc[2], io_st[2], io_ct[2];
+  // layer-pipelined LSTMP forward: one stream per layer past the first,
+  // events between them, per-(layer, chunk) step counters, per-layer
+  // exchange buffers and chunk-boundary states, chunk metadata
+  std::vector<cudaStream_t> lp_streams;
+  std::vector<cudaEvent_t> lp_events;
+  DevBuf lp_ctl, lp_hx, lp_state, lp_meta;
+  int layer_pipeline = 1;  // RCU_ATTR_LAYER_PIPELINE
   // rnn_backward: workspace, per-layer weight gradients of the last call, and
   // the forward's per-layer outputs (layer l < L-1 written to keep_out + l*T*B*Hout)
   DevBuf bw;
@@ -118,6 +122,8 @@ struct rcu_rnn_s : EventProfiler {
   }
   ~rcu_rnn_s() {
     for (auto e : chunk_ev) cudaEventDestroy(e);
+    for (auto e : lp_events) cudaEventDestroy(e);
+    for (auto st : lp_streams) cudaStreamDestroy(st);
     if (cp_in) cudaStreamDestroy(cp_in);
     if (cp_out) cudaStreamDestroy(cp_out);
   }
@@ -242,10 +248,14 @@ extern "C" int rnn_set_attr(rcu_rnn_t h, int attr, int64_t value) {
       if (value < 0 || value > 2) return fail(RCU_ERR_INVALID, "trace must be 0, 1 or 2");
       h->trace = (int)value;
       return RCU_OK;
-    case RCU_ATTR_TC_OPTIONS:
-      if (value < 0 || value > (RCU_TC_OPT_TMA_PUBLISH | RCU_TC_OPT_SHARED_COUNTER_LINE))
-        return fail(RCU_ERR_INVALID, "unknown tensor-core options %lld", (long long)value);
-      h->tc_options = (int)value;
+    case RCU_ATTR_LAYER_PIPELINE:
+      if (value != 0 && value != 1) return fail(RCU_ERR_INVALID, "layer pipeline must be 0 or 1");
+      h->layer_pipeline = (int)value;
+      return RCU_OK;
+    case RCU_ATTR_TC_COUNTER_REPLICAS:
+      if (value < 1 || value > TC_MAX_COUNTER_REPLICAS)
+        return fail(RCU_ERR_INVALID, "counter replicas must be 1 .. %d", TC_MAX_COUNTER_REPLICAS);
+      h->tc_replicas = (int)value;
       return RCU_OK;
     case RCU_ATTR_FORCE_PATH:
       if (value < 0 || value > 3) return fail(RCU_ERR_INVALID, "force_path must be 0, 1, 2 or 3");
@@ -471,6 +481,205 @@ static int ensure_ws(rcu_rnn_s *h, int T, int B) {
   return RCU_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Layer-pipelined forward of a stacked unidirectional LSTMP on the tensor-core
+// path.  A layer's recurrence on the tensor cores holds one batch group of
+// B <= 128 rows on a fraction of the GPU (64 CTAs for H = 1024), so layer l+1
+// can run steps [t0, t1) while layer l runs the next steps.  The sequence is
+// cut into chunks of steps; layer l runs its chunks in order on its own
+// stream, each chunk a launch of the folded recurrence that starts from the
+// previous chunk's final m and c (fp32) and reads the chunk's G rows.
+// Between layer l's chunk c and layer l+1's chunk c, on layer l+1's stream:
+// the projection of chunk c (h = W_hr m), its conversion to the next layer's
+// bf16 operand and the next layer's input GEMM for the chunk.  Every row of
+// these GEMMs depends only on its own inputs and every recurrent step starts
+// from the same bf16(m_{t-1}) and fp32 c_{t-1} as without chunks, so the
+// results equal the unpipelined ones.  The GEMMs that run beside a
+// recurrence use the SMs it leaves free.
+static int lp_chunks(int T) { return std::min(32, std::max(2, T / 64)); }
+
+static bool layer_pipeline_ok(rcu_rnn_t h, int T, int B, bool varlen, bool bf) {
+  if (!h->layer_pipeline || !bf || h->P == 0 || h->D != 1 || h->layers < 2 || varlen ||
+      h->pclip || h->force_path == 1 || h->trace || !h->mbuf || T < 128)
+    return false;
+  const int H = h->H, P = h->P;
+  if ((H % 8) != 0 || !tc_rec_supported(RCU_LSTM, H, H, 0, h->nsm, B, 1) ||
+      !tc_gemm_supported(H, P))
+    return false;
+  for (int l = 0; l < h->layers; ++l)
+    if (!h->lw[l].fold_w.p || !tc_gemm_supported(h->in_l[l], h->nG * H)) return false;
+  // two recurrences side by side, and room beside one of them for the GEMMs
+  const int rg = tc_rec_grid(RCU_LSTM, H, H, B, 1, h->tc_ksplit);
+  return 2 * rg <= h->nsm && h->nsm - rg >= 16;
+}
+
+static int forward_layer_pipelined(rcu_rnn_t h, int T, int B, const void *X0, int ldx0,
+                                   const float *h0, const float *c0, float *y, float *h_n,
+                                   float *c_n, int *err, cudaStream_t s) {
+  const int L = h->layers, H = h->H, P = h->P, nG = h->nG, G4 = nG * H;
+  const int ldH = round_up(H, 8);
+  const int n = lp_chunks(T);
+  const int Tc = ceil_div(T, n), nch = ceil_div(T, Tc), Tl = T - (nch - 1) * Tc;
+  const int rg = tc_rec_grid(RCU_LSTM, H, H, B, 1, h->tc_ksplit);
+  const int gemm_sms = std::max(16, h->nsm - rg);
+  const int cstride = std::max(4, tc_rec_counters(B, 1));
+  // resources
+  while ((int)h->lp_streams.size() < L - 1) {
+    cudaStream_t st;
+    CU(cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking));
+    h->lp_streams.push_back(st);
+  }
+  const int nev = L * nch + L;
+  while ((int)h->lp_events.size() < nev) {
+    cudaEvent_t e;
+    CU(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    h->lp_events.push_back(e);
+  }
+  CU(h->lp_ctl.ensure((size_t)L * nch * cstride * 4));
+  CU(h->lp_hx.ensure((size_t)L * 2 * B * ldH * 2));
+  // per layer: m and c at the chunk boundaries, ping-pong [2][B][H] each
+  CU(h->lp_state.ensure((size_t)L * 4 * B * H * 4));
+  // chunk metadata for lengths Tc and Tl (identity order)
+  const size_t meta_ints = (size_t)3 * B + 2 * (size_t)Tc + 1;
+  CU(h->lp_meta.ensure(2 * meta_ints * 4));
+  Meta mc[2];
+  for (int i = 0; i < 2; ++i) {
+    int32_t *mi = (int32_t *)h->lp_meta.p + i * meta_ints;
+    mc[i].sorted_idx = mi;
+    mc[i].unsorted_idx = mi + B;
+    mc[i].lens_sorted = mi + 2 * B;
+    mc[i].batch_sizes = mi + 3 * B;
+    mc[i].step_off = mi + 3 * B + Tc;
+  }
+  CU(cudaMemsetAsync(h->lp_ctl.p, 0, (size_t)L * nch * cstride * 4, s));
+  CU(cudaMemsetAsync(h->lp_hx.p, 0, (size_t)L * 2 * B * ldH * 2, s));
+  for (int i = 0; i < 2; ++i) {
+    h->begin("meta_sort", s);
+    CU(launch_meta(nullptr, B, i == 0 ? Tc : Tl, mc[i], err, s));
+    h->end(s);
+  }
+  // every layer's stream starts after the work already on s
+  cudaEvent_t *ev = h->lp_events.data();  // ev[l*nch + c]: layer l finished chunk c
+  cudaEvent_t *ev_done = ev + L * nch;     // ev_done[l]: layer l's stream is done
+  CU(cudaEventRecord(ev_done[0], s));
+  for (int l = 1; l < L; ++l) CU(cudaStreamWaitEvent(h->lp_streams[l - 1], ev_done[0], 0));
+  auto stream_of = [&](int l) { return l == 0 ? s : h->lp_streams[l - 1]; };
+
+  float *G = (float *)h->g;
+  __nv_bfloat16 *mbuf = (__nv_bfloat16 *)h->mbuf;
+  // layer 0's input projection for all steps at once (nothing runs beside it yet)
+  h->begin("input_gemm_tc", s);
+  {
+    cudaError_t e = launch_tc_gemm((const __nv_bfloat16 *)X0, ldx0,
+                                   (const __nv_bfloat16 *)h->wih[0].p, round_up(h->in_l[0], 8),
+                                   (const float *)h->gbias[0].p, G, G4, T * B, nullptr, G4,
+                                   h->in_l[0], h->nsm, s, err, (uint64_t)h->timeout_ns);
+    if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "tc gemm: %s", cudaGetErrorString(e));
+  }
+  h->end(s);
+  for (int c = 0; c < nch; ++c) {
+    const int t0 = c * Tc, tc = c + 1 < nch ? Tc : Tl;
+    const size_t r0 = (size_t)t0 * B;  // first packed row of the chunk
+    for (int l = 0; l < L; ++l) {
+      cudaStream_t sl = stream_of(l);
+      const bool last = l == L - 1;
+      if (l > 0) {
+        // layer l-1 finished chunk c: project it, convert, and form this
+        // layer's gate pre-activations for the chunk
+        CU(cudaStreamWaitEvent(sl, ev[(l - 1) * nch + c], 0));
+        float *Yp = h->keep_out ? h->keep_out + (size_t)(l - 1) * T * B * P : h->ytmp;
+        h->begin("projection_gemm_tc", sl);
+        cudaError_t e = launch_tc_gemm(mbuf + r0 * H, H, (const __nv_bfloat16 *)h->lw[l - 1].whr_bf.p,
+                                       ldH, nullptr, Yp + r0 * P, P, tc * B, nullptr, P, H,
+                                       gemm_sms, sl, err, (uint64_t)h->timeout_ns);
+        h->end(sl);
+        if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "projection gemm: %s", cudaGetErrorString(e));
+        if (c == nch - 1 && h_n) {
+          h->begin("last_h", sl);
+          CU(launch_last_h(Yp, P, h_n + (size_t)(l - 1) * B * P, B, T, P, 0, sl));
+          h->end(sl);
+        }
+        h->begin("convert_bf16", sl);
+        CU(launch_convert<__nv_bfloat16>(Yp + r0 * P, (__nv_bfloat16 *)h->ymid + r0 * P,
+                                         (size_t)tc * B * P, sl));
+        h->end(sl);
+        h->begin("input_gemm_tc", sl);
+        e = launch_tc_gemm((const __nv_bfloat16 *)h->ymid + r0 * P, P,
+                           (const __nv_bfloat16 *)h->wih[l].p, round_up(h->in_l[l], 8),
+                           (const float *)h->gbias[l].p, G + r0 * G4, G4, tc * B, nullptr, G4,
+                           h->in_l[l], gemm_sms, sl, err, (uint64_t)h->timeout_ns);
+        h->end(sl);
+        if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "tc gemm: %s", cudaGetErrorString(e));
+      }
+      // the layer's initial projected state enters as W_hh h0 in the first step's G
+      if (c == 0 && h0) {
+        h->begin("h0_gates", sl);
+        CU(launch_h0_gates(G, G4, (const float *)h->lw[l].whh_f32.p, h0 + (size_t)l * B * P, B,
+                           tc, G4, P, 0, sl));
+        h->end(sl);
+      }
+      float *st = (float *)h->lp_state.p + (size_t)l * 4 * B * H;  // [m0, m1, c0, c1][B][H]
+      float *m_in = st + (size_t)((c + 1) & 1) * B * H, *m_out = st + (size_t)(c & 1) * B * H;
+      float *c_in = st + (size_t)(2 + ((c + 1) & 1)) * B * H;
+      float *c_out = st + (size_t)(2 + (c & 1)) * B * H;
+      RecParams pf{};
+      pf.T = tc; pf.B = B; pf.H = H; pf.Hout = H; pf.Kp = ldH; pf.Hp = h->Hp; pf.nG = nG; pf.D = 1;
+      pf.cell = RCU_LSTM; pf.proj = 0;
+      pf.U = h->U; pf.NU = h->NU; pf.Rp = h->Rp;
+      pf.meta = mc[c + 1 < nch ? 0 : 1];
+      pf.G = G + r0 * G4;
+      pf.ldG = G4;
+      pf.bhn[0] = pf.bhn[1] = nullptr;
+      // m_{-1} does not enter the first chunk (W_hh h0 is in G); later chunks
+      // start from the previous chunk's m, rounded to bf16 by the kernel as
+      // every step's exchange is
+      pf.h0 = c == 0 ? nullptr : m_in;
+      pf.c0 = c == 0 ? (c0 ? c0 + (size_t)l * B * H : nullptr) : c_in;
+      pf.h_n = m_out;
+      pf.c_n = (c == nch - 1 && c_n) ? c_n + (size_t)l * B * H : c_out;
+      pf.y = nullptr;
+      pf.ymid = mbuf + r0 * H;
+      pf.hx = (char *)h->lp_hx.p + (size_t)l * 2 * B * ldH * 2;
+      pf.mx = h->mx; pf.hst = h->hst; pf.cst = h->cst;
+      pf.ctr = (unsigned *)h->lp_ctl.p + ((size_t)l * nch + c) * cstride;
+      pf.err = err;
+      pf.timeout_ns = (uint64_t)h->timeout_ns;
+      pf.drop_arrival = h->drop_arrival == 1 && l == 0 && c == 0;
+      pf.cclip = h->cclip; pf.cclip_lo = h->cclip_lo; pf.cclip_hi = h->cclip_hi;
+      TcRecParams tp;
+      tp.base = pf;
+      tp.ksplit = h->tc_ksplit;
+      tp.counter_replicas = h->tc_replicas;
+      tp.Wtc[0] = tp.Wtc[1] = h->lw[l].fold_w.p;
+      h->begin("recurrent_tc_lstmp", sl);
+      cudaError_t e = launch_tc_recurrent(tp, h->nsm, sl);
+      h->end(sl);
+      if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "tc recurrent: %s", cudaGetErrorString(e));
+      CU(cudaEventRecord(ev[l * nch + c], sl));
+      if (last) {
+        // the last layer's projection of the chunk, straight into y
+        h->begin("projection_gemm_tc", sl);
+        e = launch_tc_gemm(mbuf + r0 * H, H, (const __nv_bfloat16 *)h->lw[l].whr_bf.p, ldH,
+                           nullptr, y + r0 * P, P, tc * B, nullptr, P, H, gemm_sms, sl, err,
+                           (uint64_t)h->timeout_ns);
+        h->end(sl);
+        if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "projection gemm: %s", cudaGetErrorString(e));
+        if (c == nch - 1 && h_n) {
+          h->begin("last_h", sl);
+          CU(launch_last_h(y, P, h_n + (size_t)l * B * P, B, T, P, 0, sl));
+          h->end(sl);
+        }
+      }
+    }
+  }
+  // the call is complete on s once every layer's stream is
+  for (int l = 1; l < L; ++l) {
+    CU(cudaEventRecord(ev_done[l], h->lp_streams[l - 1]));
+    CU(cudaStreamWaitEvent(s, ev_done[l], 0));
+  }
+  return RCU_OK;
+}
+
 extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int32_t *lengths,
                            const float *h0, const float *c0, const float *eps, float *y,
                            float *h_n, float *c_n, void *stream) {
@@ -542,6 +751,10 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
     X = h->xp;
   }
   h->used_tc_gemm = h->used_tc_rec = false;
+  if (layer_pipeline_ok(h, T, B, varlen, bf)) {
+    h->used_tc_gemm = h->used_tc_rec = true;
+    return forward_layer_pipelined(h, T, B, X, ldx, h0, c0, y, h_n, c_n, err, s);
+  }
   for (int l = 0; l < h->layers; ++l) {
     const int K = h->in_l[l];
     const int ldw = round_up(K, 8);
@@ -635,7 +848,7 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
       TcRecParams tp;
       tp.base = pf;
       tp.ksplit = h->tc_ksplit;
-      tp.options = h->tc_options;
+      tp.counter_replicas = h->tc_replicas;
       for (int d = 0; d < D; ++d) tp.Wtc[d] = h->lw[(size_t)l * D + d].fold_w.p;
       h->begin("recurrent_tc_lstmp", s);
       cudaError_t e = launch_tc_recurrent(tp, h->nsm, s);
@@ -687,7 +900,7 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
       TcRecParams tp;
       tp.base = p;
       tp.ksplit = h->tc_ksplit;
-      tp.options = h->tc_options;
+      tp.counter_replicas = h->tc_replicas;
       for (int d = 0; d < D; ++d) tp.Wtc[d] = h->lw[(size_t)l * D + d].tc_whh.p;
       cudaError_t e = launch_tc_recurrent(tp, h->nsm, s);
       if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "tc recurrent: %s", cudaGetErrorString(e));

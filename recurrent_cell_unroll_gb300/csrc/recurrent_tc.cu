@@ -44,10 +44,7 @@ constexpr int MAX_STAGES = 8;
 struct Maps {
   CUtensorMap hx;    // [D*2*B rows][K cols], ld Kp, bf16, box 64 x a_rows
   CUtensorMap w[2];  // per direction [NU16*nG*16 rows][K cols], ld Kp, bf16, box 64 x N
-  // the same exchange buffer as [D*2 planes][B rows][Hout cols], box 16 x 128 x 1
-  // (no swizzle): h_t tiles stored by TMA (TC_OPT_TMA_PUBLISH)
-  CUtensorMap hxs;
-  int opts;          // RCU_ATTR_TC_OPTIONS bits
+  int reps;          // replicas of each step counter (1 .. TC_MAX_COUNTER_REPLICAS)
   // h rows loaded per stage: 128, or round_up(B, 8) when one batch group
   // holds the whole batch (the stage's other rows are never read back: a
   // row of D depends only on the same row of A, and the epilogue skips rows
@@ -74,7 +71,7 @@ struct Ctl {
 // memory).
 struct Geo {
   int N, nkb, nkbm, stages;
-  size_t w_bytes, x_bytes, t_bytes, smem;
+  size_t w_bytes, x_bytes, smem;
 };
 
 __host__ __device__ inline Geo make_geo(int nG, int K, int KS) {
@@ -85,9 +82,7 @@ __host__ __device__ inline Geo make_geo(int nG, int K, int KS) {
   g.w_bytes = (size_t)g.nkbm * g.N * 128;
   // partial sums received from the other KS-1 CTAs: [KS-1][nG][4][128] float4
   g.x_bytes = (size_t)(KS - 1) * nG * 4 * BG * 16;
-  // h_t tile of the CTA's 16 units, bf16 [128 rows][16], staged for a TMA store
-  g.t_bytes = (size_t)BG * UNITS * 2;
-  const size_t fixed = 1024 + g.w_bytes + g.x_bytes + g.t_bytes + 256;
+  const size_t fixed = 1024 + g.w_bytes + g.x_bytes + 256;
   int st = (int)((SMEM_LIMIT - (long long)fixed) / A_STAGE);
   g.stages = st > MAX_STAGES ? MAX_STAGES : st;
   g.smem = fixed + (size_t)(g.stages > 0 ? g.stages : 0) * A_STAGE;
@@ -96,22 +91,6 @@ __host__ __device__ inline Geo make_geo(int nG, int K, int KS) {
 
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_shared() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-// TMA store of a shared-memory tile to the 3D tensor at (x, y, z); the caller
-// commits and waits for it
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *smem_src, int x,
-                                             int y, int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(map)),
-      "r"(tc::smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit_wait_all() {
-  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
 }
 // Step trace: CTA 0's stamps for every step, and (RCU_ATTR_TRACE = 2) every
 // CTA's stamps for a window of steps.  Called by one thread per stamp.
@@ -163,9 +142,7 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
   uint8_t *sW = smem;                       // resident B operand, nkbm blocks of N x 128 B
   uint8_t *sA = smem + geo.w_bytes;         // ring of STG stages of 128 x 128 B
   float4 *xbuf = reinterpret_cast<float4 *>(sA + (size_t)STG * A_STAGE);
-  __nv_bfloat16 *htile =
-      reinterpret_cast<__nv_bfloat16 *>(reinterpret_cast<uint8_t *>(xbuf) + geo.x_bytes);
-  Ctl *ctl = reinterpret_cast<Ctl *>(reinterpret_cast<uint8_t *>(htile) + geo.t_bytes);
+  Ctl *ctl = reinterpret_cast<Ctl *>(reinterpret_cast<uint8_t *>(xbuf) + geo.x_bytes);
 
   const int NU = p.NU, NBG = ceil_div(p.B, BG);  // NU = CTAs per (direction, batch group)
   const int d = blockIdx.x / (NBG * NU);
@@ -186,12 +163,13 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
   // that ordering is what lets the partial-sum buffer be reused step after
   // step and bounds the sends in flight to one step.  (Waiting only for the
   // producers of a CTA's own K share would break it.)
-  // (each counter on its own 128-byte line, away from the error word, unless
-  // TC_OPT_SHARED_LINE asks for the packed layout)
-  unsigned *ctr = (maps.opts & TC_OPT_SHARED_LINE)
-                      ? p.ctr + (size_t)(d * NBG + bg)
-                      : p.ctr + (size_t)(d * NBG + bg) * 32 + 16;
-  unsigned *ctr_arrive = ctr;
+  // The counter is replicated maps.reps times, each replica on its own
+  // 128-byte line: every CTA adds to every replica (one lane per replica) and
+  // polls one of them, so no line has more than NU / reps pollers.  (With all
+  // NU CTAs polling one line, the last arrival took up to 2.8 us to reach
+  // every poller.)
+  unsigned *ctr_rep = p.ctr + (size_t)(d * NBG + bg) * (TC_MAX_COUNTER_REPLICAS * 32) + 16;
+  unsigned *ctr = ctr_rep + (size_t)(cu % maps.reps) * 32;  // the replica this CTA polls
   const unsigned n_wait = (unsigned)NU;
   // steps this batch group runs: the longest row of the group (rows sorted by length)
   const int Tg = row0 < B ? p.meta.lens_sorted[row0] : 0;
@@ -367,7 +345,6 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
       }
     }
     int x_posted = 0, x_done = 0;  // K split, thread 64: phases armed / completed
-    const bool tma_pub = (maps.opts & TC_OPT_TMA_PUBLISH) != 0;
     float h[UPT], c[UPT], bn[UPT];
     int b = 0, len = 0;
     if (row_ok) {
@@ -389,8 +366,9 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
     }
     fence_proxy_async_global();
     epi_bar();
-    if (threadIdx.x == 64) {
-      red_release_gpu_add(ctr_arrive, (p.drop_arrival && blockIdx.x == 0) ? 0u : 1u);
+    if (threadIdx.x >= 64 && threadIdx.x < 64 + maps.reps) {
+      red_release_gpu_add(ctr_rep + (size_t)(threadIdx.x - 64) * 32,
+                          (p.drop_arrival && blockIdx.x == 0) ? 0u : 1u);
     }
     for (int step = 0; step < Tg; ++step) {
       const bool active = row_ok && step < len;
@@ -492,18 +470,7 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
         }
       }
       // exchange buffer for the next step (bf16 MMA operand): on the critical path
-      if (tma_pub) {
-        // the CTA's h_t tile goes out as one TMA store (rows past B and units
-        // past Hout are clipped by the tensor map; rows past their length
-        // carry their last state, which no active row reads)
-        __nv_bfloat162 lo = __floats2bfloat162_rn(nu > 0 ? h[0] : 0.f, nu > 1 ? h[1] : 0.f);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(nu > 2 ? h[2] : 0.f, nu > 3 ? h[3] : 0.f);
-        uint2 pk;
-        pk.x = *reinterpret_cast<uint32_t *>(&lo);
-        pk.y = *reinterpret_cast<uint32_t *>(&hi);
-        *reinterpret_cast<uint2 *>(htile + r * UNITS + part * UPT) = pk;
-        fence_proxy_async_shared();
-      } else if (active) {
+      if (active) {
         __nv_bfloat16 *dst = hx + (size_t)(((step & 1) ^ 1) * B + s) * Kp + ub;
         if (nu == UPT) {
           __nv_bfloat162 lo = __floats2bfloat162_rn(h[0], h[1]);
@@ -519,19 +486,14 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
         }
       }
       if (p.trace && threadIdx.x == 64) stamp(p, step, 6, globaltimer_ns());
-      if (!tma_pub) fence_proxy_async_global();
+      fence_proxy_async_global();
       epi_bar();
-      if (threadIdx.x == 64) {
-        if (p.trace) stamp(p, step, 7, globaltimer_ns());
-        if (tma_pub && u0 < p.Hout) {
-          // the store completes (wait_group 0: its writes performed) before the
-          // release; the proxy fence orders those async-proxy writes with it
-          tma_store_3d(&maps.hxs, htile, u0, row0, d * 2 + ((step & 1) ^ 1));
-          bulk_commit_wait_all();
-          fence_proxy_async_global();
-        }
-        red_release_gpu_add(ctr_arrive, 1u);  // release: orders the epilogue's h_t stores
-        if (p.trace) stamp(p, step, 4, globaltimer_ns());
+      if (threadIdx.x >= 64 && threadIdx.x < 64 + maps.reps) {
+        if (p.trace && threadIdx.x == 64) stamp(p, step, 7, globaltimer_ns());
+        // release: orders the epilogue's h_t stores (all threads, through the
+        // barrier above) before the arrival on replica threadIdx.x - 64
+        red_release_gpu_add(ctr_rep + (size_t)(threadIdx.x - 64) * 32, 1u);
+        if (p.trace && threadIdx.x == 64) stamp(p, step, 4, globaltimer_ns());
       }
       // outputs leave the critical path: written after h_t is published
       if (active && p.y) {
@@ -639,20 +601,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [planes][rows][cols] bf16 (row stride ld elements), box cols_box x rows_box x 1, no swizzle
-bool make_map3(CUtensorMap *map, const void *base, int planes, int rows, int cols, int ld,
-               int cols_box, int rows_box) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)planes};
-  cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)ld * 2 * rows};
-  cuuint32_t box[3] = {(cuuint32_t)cols_box, (cuuint32_t)rows_box, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool make_map(CUtensorMap *map, const void *base, long long rows, int cols, int ld, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -682,7 +630,21 @@ bool tc_rec_supported(int cell, int H, int Hout, int P, int nsm, int B, int D) {
   return ctas <= nsm;
 }
 
-int tc_rec_counters(int B, int D) { return D * ceil_div(B, BG) * 32 + 32; }
+int tc_rec_counters(int B, int D) {
+  return D * ceil_div(B, BG) * TC_MAX_COUNTER_REPLICAS * 32 + 32;
+}
+
+namespace {
+bool ks_fits(int nG, int K, int ks);
+}
+
+int tc_rec_grid(int cell, int H, int Hout, int B, int D, int ksplit) {
+  const int nG = cell == CELL_LSTM ? 4 : 3;
+  int ks = ksplit == 0 ? 2 : ksplit;
+  while (ks > 1 && !ks_fits(nG, Hout, ks)) ks /= 2;
+  const int NU = ks > 1 ? ks * ceil_div(H, ks * UNITS) : ceil_div(H, UNITS);
+  return D * ceil_div(B, BG) * NU;
+}
 
 void tc_pack_whh(int cell, int H, int Hout, const float *whh, std::vector<uint16_t> &out,
                  uint16_t (*to_bf16)(float)) {
@@ -751,9 +713,7 @@ cudaError_t launch_tc_recurrent(const TcRecParams &tp, int nsm, cudaStream_t s) 
   maps.a_rows = NBG == 1 ? round_up(p.B, 8) : BG;
   if (!make_map(&maps.hx, p.hx, (long long)p.D * 2 * p.B, p.Hout, p.Kp, maps.a_rows))
     return cudaErrorInvalidValue;
-  maps.opts = tp.options;
-  if (!make_map3(&maps.hxs, p.hx, p.D * 2, p.B, p.Hout, p.Kp, UNITS, maps.a_rows))
-    return cudaErrorInvalidValue;
+  maps.reps = std::min(std::max(tp.counter_replicas, 1), TC_MAX_COUNTER_REPLICAS);
 
   // K split over ks CTAs (a cluster): requested (1, 2 or 4), or automatic (a
   // pair); halved until the plan fits shared memory and gives every CTA a K block

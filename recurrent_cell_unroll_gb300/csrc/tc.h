@@ -18,9 +18,8 @@ cudaError_t launch_tc_gemm(const __nv_bfloat16 *X, int ldx, const __nv_bfloat16 
                            const float *bias, float *G, int ldg, int M, const int32_t *M_dev,
                            int N, int K, int nsm, cudaStream_t s, int *err, uint64_t timeout_ns);
 
-// RCU_ATTR_TC_OPTIONS bits (the same values as rcu.h's RCU_TC_OPT_*)
-constexpr int TC_OPT_TMA_PUBLISH = 1;  // h_t tile published by a TMA store
-constexpr int TC_OPT_SHARED_LINE = 2;  // step counters packed on one line (old layout)
+// most replicas of a step counter (RCU_ATTR_TC_COUNTER_REPLICAS)
+constexpr int TC_MAX_COUNTER_REPLICAS = 16;
 
 // ---- recurrent_tc.cu: persistent recurrent kernel with the per-step
 // h W_hh^T on tcgen05.
@@ -28,14 +27,16 @@ struct TcRecParams {
   RecParams base;
   const void *Wtc[2];  // tensor-core packed W_hh per direction (tc_pack_whh)
   int ksplit = 0;      // CTAs splitting K: 0 = automatic (2), 1 = none, 2 or 4 = a cluster
-  int options = 0;     // RCU_ATTR_TC_OPTIONS bits (see rcu.h)
+  int counter_replicas = 8;  // replicas of each step counter (RCU_ATTR_TC_COUNTER_REPLICAS)
 };
 // weights can be packed for the tensor-core kernel (shape only)
 bool tc_rec_packable(int cell, int H, int Hout, int P);
 // the kernel can run this forward (co-resident grid for B rows, D directions)
 bool tc_rec_supported(int cell, int H, int Hout, int P, int nsm, int B, int D);
-// barrier counter words one layer needs (each counter on its own 128-byte line)
+// barrier counter words one layer needs (each replica on its own 128-byte line)
 int tc_rec_counters(int B, int D);
+// CTAs of the kernel's first-choice plan (K split as requested or automatic)
+int tc_rec_grid(int cell, int H, int Hout, int B, int D, int ksplit);
 void tc_pack_whh(int cell, int H, int Hout, const float *whh, std::vector<uint16_t> &out,
                  uint16_t (*to_bf16)(float));
 cudaError_t launch_tc_recurrent(const TcRecParams &p, int nsm, cudaStream_t s);

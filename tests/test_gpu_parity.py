@@ -240,18 +240,17 @@ KSPLIT = [
 
 @pytest.mark.parametrize("spec", KSPLIT, ids=lambda s: f"{s.name}-T{s.T}-B{s.B}-H{s.hidden}")
 @pytest.mark.parametrize("ksplit", [1, 2, 4])
-@pytest.mark.parametrize("options", [0, 1, 3], ids=["opt0", "tma_publish", "tma_shared_line"])
-def test_tensor_core_k_split(spec, ksplit, options):
+@pytest.mark.parametrize("replicas", [1, 8, 16])
+def test_tensor_core_k_split(spec, ksplit, replicas):
     """h W_hh^T with K kept whole (1) or split over a CTA pair (2) or four
     CTAs (4) whose partial sums are exchanged through distributed shared
-    memory; h_t published by per-thread stores or by one TMA store per CTA,
-    step counters on their own lines or packed on one."""
+    memory; each step counter kept once or replicated 8 or 16 times."""
     inp = wl.make_rnn_inputs(spec, seed=17)
     dev = torch.device("cuda")
     net = binding.RNN.from_spec(spec)
     net.set_attr(binding.RCU_ATTR_FORCE_PATH, 2)
     net.set_attr(binding.RCU_ATTR_TC_KSPLIT, ksplit)
-    net.set_attr(binding.RCU_ATTR_TC_OPTIONS, options)
+    net.set_attr(binding.RCU_ATTR_TC_COUNTER_REPLICAS, replicas)
     net.set_attr(binding.RCU_ATTR_PROFILE, 1)
     net.set_weights(inp["weights"])
     lengths = inp["lengths"].to(dev) if inp["lengths"] is not None else None
@@ -264,6 +263,42 @@ def test_tensor_core_k_split(spec, ksplit, options):
     got = (y.cpu().numpy(), hn.cpu().numpy(), None if cn is None else cn.cpu().numpy())
     compare(spec, got, run_oracle(spec, inp))
     net.close()
+
+
+# Layer-pipelined LSTMP (unidirectional, bf16, T >= 128): layers run
+# concurrently over chunks of steps; ragged last chunk; three layers
+PIPE = [
+    wl.LSTMP_2L.scaled(T=200, B=32, in_dim=80, hidden=256, proj=64, h0_std=0.5, c0_std=0.5),
+    wl.LSTMP_2L.scaled(layers=3, T=131, B=7, in_dim=24, hidden=128, proj=48),
+]
+
+
+@pytest.mark.parametrize("spec", PIPE, ids=lambda s: f"L{s.layers}-T{s.T}-B{s.B}-H{s.hidden}")
+def test_layer_pipelined_lstmp(spec):
+    """The pipelined forward equals the layer-by-layer one bit for bit (every
+    GEMM row and recurrent step sees the same operands) and the oracle."""
+    inp = wl.make_rnn_inputs(spec, seed=23)
+    dev = torch.device("cuda")
+    outs = []
+    for pipe in (1, 0):
+        net = binding.RNN.from_spec(spec)
+        net.set_attr(binding.RCU_ATTR_LAYER_PIPELINE, pipe)
+        net.set_attr(binding.RCU_ATTR_PROFILE, 1)
+        net.set_weights(inp["weights"])
+        h0 = inp["h0"].to(dev) if inp["h0"] is not None else None
+        c0 = inp["c0"].to(dev) if inp["c0"] is not None else None
+        y, hn, cn = net.forward(inp["x"].to(dev), h0=h0, c0=c0)
+        assert net.status() == 0
+        torch.cuda.synchronize()
+        prof = net.profile()
+        # one recurrent launch per layer and chunk when pipelined, per layer otherwise
+        n_rec = prof["recurrent_tc_lstmp"][1]
+        assert (n_rec > spec.layers) if pipe else (n_rec == spec.layers), prof
+        outs.append((y.cpu().numpy(), hn.cpu().numpy(), cn.cpu().numpy()))
+        net.close()
+    for a, b in zip(*outs):
+        np.testing.assert_array_equal(a, b)
+    compare(spec, outs[0], run_oracle(spec, inp))
 
 
 CLUSTER = [
