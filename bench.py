@@ -37,6 +37,7 @@ WORKLOADS = {
     "lstm": wl.LSTM_T80, "rssm": wl.RSSM_B50, "lstmp": wl.LSTMP_2L,
     "bilstm": wl.BILSTM_VAR, "gru": wl.GRU_3L, "rssm_actor": wl.RSSM_ACTOR,
     "lstm_train": wl.LSTM_TRAIN, "bilstm_train": wl.BILSTM_TRAIN, "rssm_train": wl.RSSM_TRAIN,
+    "gru_train": wl.GRU_TRAIN,
 }
 METRIC = "(batch×timesteps)/s"
 UNIT = "(B·T)/s"
@@ -842,28 +843,57 @@ def oracle_serial(spec) -> bool:
     return isinstance(spec, wl.RssmSpec) and spec.train
 
 
-def sample_rows(spec, inp, cores, budget_s):
-    """Rows for a bounded oracle sample: at most one per core (any number for a
-    one-thread oracle), at least one; when a single row already exceeds the
-    budget, one row."""
-    per_row = oracle_sample(spec, inp, [0], 1)
+def prefix(spec, inp, Tp):
+    """The workload cut to its first Tp steps (every step of a recurrence
+    costs the same, so (B*T)/s of the prefix is that of the whole)."""
+    if Tp >= spec.T:
+        return spec, inp
+    out = dict(inp)
+    if isinstance(spec, wl.RssmSpec):
+        for k in ("actions", "eps", "dmeans", "dstds", "dstates", "dbeliefs"):
+            if out.get(k) is not None:
+                out[k] = out[k][:Tp]
+    else:
+        out["x"] = inp["x"][:Tp]
+        if inp.get("dy") is not None:
+            out["dy"] = inp["dy"][:Tp]
+        if inp.get("lengths") is not None:
+            out["lengths"] = inp["lengths"].clamp(max=Tp)
+    return spec.scaled(T=Tp), out
+
+
+def sample_plan(spec, inp, cores, budget_s):
+    """(rows, steps) of a bounded oracle sample: one row timed over a short
+    prefix gives the cost of a row-step; then as many rows as the budget
+    allows over all steps (at most one per core unless the oracle is
+    serial), or, when a whole row exceeds the budget, one row over the
+    longest prefix that fits."""
+    T0 = min(spec.T, 16)
+    sp, ip = prefix(spec, inp, T0)
+    per_step = oracle_sample(sp, ip, [0], 1) / T0
     par = 1 if oracle_serial(spec) else cores
     cap = spec.B if oracle_serial(spec) else cores
-    n = max(1, min(spec.B, cap, int(budget_s * par / max(per_row, 1e-9))))
-    return list(range(n)), per_row
+    per_row = per_step * spec.T
+    if per_row <= budget_s * par:
+        n = max(1, min(spec.B, cap, int(budget_s * par / max(per_row, 1e-9))))
+        return list(range(n)), spec.T
+    return [0], max(1, min(spec.T, int(budget_s / max(per_step, 1e-9))))
 
 
 def cpu_baseline(spec, inp, budget_s=20.0):
     import oracle
     oracle.build()
     cores = cpu_cores()
-    rows, _ = sample_rows(spec, inp, cores, budget_s)
+    rows, Tp = sample_plan(spec, inp, cores, budget_s)
+    sp, ip = prefix(spec, inp, Tp)
     threads = 1 if oracle_serial(spec) else min(cores, len(rows))
-    t = oracle_sample(spec, inp, rows, threads)
-    value = len(rows) * spec.T / t
+    t = oracle_sample(sp, ip, rows, threads)
+    value = len(rows) * Tp / t
+    steps = f"all {spec.T} steps" if Tp == spec.T else f"the first {Tp} of {spec.T} steps"
     return {"value": round(value, 3), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{len(rows)} of {spec.B} batch rows, all {spec.T} steps and layers "
-                      f"(rows are independent), fp64, {threads} threads",
+            "sample": f"{len(rows)} of {spec.B} batch rows, {steps}, all layers "
+                      f"(rows are independent, every step costs the same), fp64, "
+                      f"{threads} threads",
             "seconds": round(t, 3)}
 
 
@@ -875,15 +905,17 @@ def run_reference(args, spec):
     cores = cpu_cores()
     # size each step so that warm-up + timed steps stay within ~3 minutes
     budget = max(1.0, min(20.0, 180.0 / max(1, args.steps + args.warmup)))
-    rows, _ = sample_rows(spec, inp, cores, budget)
+    rows, Tp = sample_plan(spec, inp, cores, budget)
+    sp, ip = prefix(spec, inp, Tp)
     threads = 1 if oracle_serial(spec) else min(cores, len(rows))
     for _ in range(args.warmup):
-        oracle_sample(spec, inp, rows, threads)
+        oracle_sample(sp, ip, rows, threads)
     t = 0.0
     for _ in range(args.steps):
-        t += oracle_sample(spec, inp, rows, threads)
-    value = len(rows) * spec.T * args.steps / t
-    sample = (f"{len(rows)} of {spec.B} batch rows per step, all {spec.T} steps and layers, "
+        t += oracle_sample(sp, ip, rows, threads)
+    value = len(rows) * Tp * args.steps / t
+    steps = f"all {spec.T} steps" if Tp == spec.T else f"the first {Tp} of {spec.T} steps"
+    sample = (f"{len(rows)} of {spec.B} batch rows per step, {steps}, all layers, "
               f"fp64, {threads} threads")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
@@ -902,9 +934,12 @@ def run_reference(args, spec):
 
 # The shapes the metric is also quoted on, measured after the headline
 # workload in the same run (1 GPU only): the TVM page's LSTM, the RSSM prior,
-# the 2-layer LSTMP, the variable-length bidirectional LSTM, and the RSSM with
-# the actor in the loop.
-CONFIG_WORKLOADS = ("lstm", "rssm", "lstmp", "bilstm", "rssm_actor")
+# the 2-layer LSTMP, the variable-length bidirectional LSTM, the RSSM with
+# the actor in the loop, and the training passes (forward + backward through
+# time) of the LSTM, the variable-length bidirectional LSTM, the RSSM and the
+# 3-layer GRU.
+CONFIG_WORKLOADS = ("lstm", "rssm", "lstmp", "bilstm", "rssm_actor", "lstm_train",
+                    "bilstm_train", "rssm_train", "gru_train")
 
 
 def run_configs(args, rank, local, ws):

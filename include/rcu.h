@@ -306,7 +306,7 @@ RCU_API int rnn_profile_reset(rcu_rnn_t h);
  * unused).  Tensor-core kernel slots: 0 producer saw the step barrier,
  * 1 first h stage landed, 8 last h stage landed, 2 last MMA issued,
  * 3 epilogue got the accumulator, 5 accumulator read, 11 partner CTA's
- * partial sums received (K split only), 6 gates done and h_t stored,
+ * partial sums received (K split only), 13 gates done, 6 h_t stored,
  * 7 epilogue threads joined, 4 h_t published; slots 9 and 10 hold the MMA
  * thread's clock cycles spent waiting for and issuing h stages.  Portable kernel
  * slots: 0 step start, 1 gates done, 2 barrier passed.  With RCU_ATTR_TRACE

@@ -70,6 +70,9 @@ __global__ void bwd_prep_kernel(int T, int B, int H, int cell, float *__restrict
 }
 
 constexpr int UMAX = 16;  // hidden units per CTA (register tile width)
+// dynamic shared memory of the reverse-time kernel: the opt-in per-block
+// limit (227 KB) less room for its static shared memory (the barrier flag)
+constexpr size_t SMEM_CAP = 227 * 1024 - 64;
 
 // a row length clamped to [1, T] (the forward flags out-of-range lengths in
 // the status word and runs them clamped the same way)
@@ -353,12 +356,19 @@ RecPlan plan_rec(int H, int B, int nG, int nsm) {
     r.Gp = round_up(nG * H, 4);
     const int RG = ceil_div(r.BS, 4);
     if (r.U > UMAX || RG > NT || r.NUG * nbg > nsm) continue;
-    r.KS = std::max(1, std::min(32, NT / RG));
-    r.KC = std::min(512, round_up(r.Gp, 4 * r.KS));
-    while (r.KC > 4 * r.KS && rec_smem(r.U, r.Gp, r.BS, r.KC, r.KS) > (size_t)227 * 1024)
-      r.KC -= 4 * r.KS;
-    r.smem = rec_smem(r.U, r.Gp, r.BS, r.KC, r.KS);
-    if (r.smem > (size_t)227 * 1024) continue;
+    // K slices per row group: as many as the threads allow, halved while the
+    // slices' partial tiles (KS * BS * U floats) keep the plan from fitting
+    // (the 256-row, 1024-unit GRU fits with 4)
+    bool fits = false;
+    for (r.KS = std::max(1, std::min(32, NT / RG)); r.KS >= 1 && !fits; r.KS /= 2) {
+      r.KC = std::min(512, round_up(r.Gp, 4 * r.KS));
+      while (r.KC > 4 * r.KS && rec_smem(r.U, r.Gp, r.BS, r.KC, r.KS) > SMEM_CAP)
+        r.KC -= 4 * r.KS;
+      r.smem = rec_smem(r.U, r.Gp, r.BS, r.KC, r.KS);
+      fits = r.smem <= SMEM_CAP;
+      if (fits) break;
+    }
+    if (!fits) continue;
     const long long traffic = (long long)nbg * r.NUG * r.BS;
     if (best_traffic < 0 || traffic < best_traffic) {
       best = r;

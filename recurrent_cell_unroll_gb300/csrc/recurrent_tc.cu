@@ -370,24 +370,30 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
       red_release_gpu_add(ctr_rep + (size_t)(threadIdx.x - 64) * 32,
                           (p.drop_arrival && blockIdx.x == 0) ? 0u : 1u);
     }
+    // the input projection G of step st for this thread's row and units
+    // (loaded a whole step ahead of its use: right after the previous step's
+    // gates, so its latency is off the critical path)
+    float gx[NG][UPT];
+    auto load_g = [&](int st) {
+      if (!(row_ok && st < len)) return;
+      const int tg = d == 0 ? st : len - 1 - st;
+      const size_t grow = (size_t)p.meta.step_off[tg] + s;
+      const float *gp = p.G + grow * p.ldG + (size_t)d * NG * H + ub;
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        if (vec_g) {
+          const float4 f = __ldg(reinterpret_cast<const float4 *>(gp + (size_t)g * H));
+          gx[g][0] = f.x; gx[g][1] = f.y; gx[g][2] = f.z; gx[g][3] = f.w;
+        } else {
+#pragma unroll
+          for (int j = 0; j < UPT; ++j) gx[g][j] = j < nu ? __ldg(gp + (size_t)g * H + j) : 0.f;
+        }
+      }
+    };
+    load_g(0);
     for (int step = 0; step < Tg; ++step) {
       const bool active = row_ok && step < len;
       const int tt = d == 0 ? step : len - 1 - step;
-      float gx[NG][UPT];
-      if (active) {
-        const size_t grow = (size_t)p.meta.step_off[tt] + s;
-        const float *gp = p.G + grow * p.ldG + (size_t)d * NG * H + ub;
-#pragma unroll
-        for (int g = 0; g < NG; ++g) {
-          if (vec_g) {
-            const float4 f = __ldg(reinterpret_cast<const float4 *>(gp + (size_t)g * H));
-            gx[g][0] = f.x; gx[g][1] = f.y; gx[g][2] = f.z; gx[g][3] = f.w;
-          } else {
-#pragma unroll
-            for (int j = 0; j < UPT; ++j) gx[g][j] = j < nu ? __ldg(gp + (size_t)g * H + j) : 0.f;
-          }
-        }
-      }
       // one thread waits for the accumulator; its result is shared so that
       // all epilogue threads leave the loop together
       if (threadIdx.x == 64) ctl->go = tc::mbar_wait(&ctl->tfull, step & 1, p.err, abort, tmo);
@@ -469,6 +475,8 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
           }
         }
       }
+      if (p.trace && threadIdx.x == 64) stamp(p, step, 13, globaltimer_ns());
+      load_g(step + 1);
       // exchange buffer for the next step (bf16 MMA operand): on the critical path
       if (active) {
         __nv_bfloat16 *dst = hx + (size_t)(((step & 1) ^ 1) * B + s) * Kp + ub;

@@ -34,6 +34,8 @@ PHASES = {
                      (8, 3, "last stage -> epilogue has the accumulator"),
                      (3, 5, "TMEM read (and partial sums sent)"),
                      (5, 11, "partner's partial sums received"),
+                     (11, 13, "gates"),
+                     (13, 6, "next step's G loads issued, h_t stored"),
                      (5, 6, "-> gates done, h_t stored"),
                      (6, 4, "h_t published")],
     "recurrent_simt": [(0, 3, "h_{t-1} rows loaded"), (3, 4, "mat-vec"),

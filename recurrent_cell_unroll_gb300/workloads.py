@@ -101,8 +101,13 @@ LSTM_TRAIN = RnnSpec("lstm_train_f32_T500_B64_256x512", "lstm", 1, 256, 512, T=5
 # itself (the same x, lengths and weights as BILSTM_VAR; dy ~ N(0, 1))
 BILSTM_TRAIN = BILSTM_VAR.scaled(name="bilstm_train_f32_varlen_B64_T500_256x512", train=True)
 
+# forward + backward through time of the 3-layer GRU itself (its x, h0 and
+# weights; dy ~ N(0, 1)): the bf16 forward, the fp32 gradient of the model
+# with the bf16-rounded weights
+GRU_TRAIN = GRU_3L.scaled(name="gru_train_bf16_3L_T512_B256_1024", train=True)
+
 WORKLOADS = {s.name: s for s in (LSTM_T80, RSSM_B50, LSTMP_2L, BILSTM_VAR, GRU_3L,
-                                  RSSM_ACTOR, LSTM_TRAIN, BILSTM_TRAIN, RSSM_TRAIN)}
+                                  RSSM_ACTOR, LSTM_TRAIN, BILSTM_TRAIN, RSSM_TRAIN, GRU_TRAIN)}
 
 
 def _uniform(g, shape, bound):

@@ -217,3 +217,25 @@ def test_bf16_peak_choice_follows_the_timed_region():
     assert bench.bf16_peak(peaks, 0.3)[0] == 1900.0
     assert bench.bf16_peak(peaks, None)[0] == 1900.0
     assert bench.bf16_peak(peaks, 5.0)[0] == 1700.0
+
+
+def test_oracle_sample_prefix_and_plan():
+    """A bounded CPU sample cuts the workload to a prefix of its steps (the
+    varlen lengths clamped, the training gradients cut too) and sizes rows x
+    steps to the budget: a row that does not fit becomes one row over fewer
+    steps."""
+    spec = wl.BILSTM_TRAIN.scaled(T=30, B=4, in_dim=8, hidden=8, varlen=(5, 30))
+    inp = wl.make_rnn_inputs(spec, seed=1)
+    sp, ip = bench.prefix(spec, inp, 7)
+    assert sp.T == 7 and ip["x"].shape[0] == 7 and ip["dy"].shape[0] == 7
+    assert int(ip["lengths"].max()) <= 7 and inp["lengths"].max() > 7
+    assert bench.prefix(spec, inp, 30)[0] is spec
+    rows, Tp = bench.sample_plan(spec, inp, cores=2, budget_s=60.0)
+    assert Tp == spec.T and 1 <= len(rows) <= 2
+    rows, Tp = bench.sample_plan(spec, inp, cores=2, budget_s=1e-9)
+    assert rows == [0] and Tp == 1
+    cb = bench.cpu_baseline(spec, inp, budget_s=0.5)
+    assert cb["value"] > 0 and cb["kind"] == "oracle"
+    rs = wl.RSSM_TRAIN.scaled(T=9, B=3)
+    sp, ip = bench.prefix(rs, wl.make_rssm_inputs(rs, seed=2), 4)
+    assert sp.T == 4 and ip["eps"].shape[0] == 4 and ip["dbeliefs"].shape[0] == 4

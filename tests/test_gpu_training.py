@@ -114,6 +114,9 @@ BWD_BF16_SPECS = [
     wl.LSTM_T80.scaled(T=9, B=6, in_dim=24, hidden=40, dtype="bf16", h0_std=0.5, c0_std=0.5),
     wl.LSTMP_2L.scaled(T=7, B=5, in_dim=24, hidden=64, proj=16),        # folded forward
     wl.LSTM_T80.scaled(T=9, B=6, in_dim=24, hidden=40, dtype="bf16", varlen=(1, 9)),
+    # the 3-layer GRU workload's width: 1024 units, 256 rows (the reverse-time
+    # kernel's plan shrinks its K slices to fit), short T, one layer
+    wl.GRU_3L.scaled(T=3, B=256, in_dim=64, hidden=1024, layers=1, h0_std=0.1),
 ]
 
 
