@@ -278,7 +278,7 @@ def make_rssm_train_runner(spec, inp, dev):
     return step, launches, profile_on, profile_read, e2e_io, status, m
 
 
-def make_runner(spec, inp, dev, tc_ksplit=0, tc_replicas=0):
+def make_runner(spec, inp, dev, tc_ksplit=0):
     from recurrent_cell_unroll_gb300 import binding
     if isinstance(spec, wl.RssmSpec) and spec.train:
         return make_rssm_train_runner(spec, inp, dev)
@@ -332,8 +332,6 @@ def make_runner(spec, inp, dev, tc_ksplit=0, tc_replicas=0):
     net = binding.RNN.from_spec(spec)
     if tc_ksplit:
         net.set_attr(binding.RCU_ATTR_TC_KSPLIT, tc_ksplit)
-    if tc_replicas:
-        net.set_attr(binding.RCU_ATTR_TC_COUNTER_REPLICAS, tc_replicas)
     net.set_weights(inp["weights"], device=dev)
     d = {k: (None if inp[k] is None else inp[k].to(dev)) for k in ("x", "lengths", "h0", "c0")}
     T, B = spec.T, spec.B
@@ -527,7 +525,7 @@ def run_ours(args, spec, rank, local, ws):
     inp = (wl.make_rssm_inputs(spec, seed=args.seed + rank) if isinstance(spec, wl.RssmSpec)
            else wl.make_rnn_inputs(spec, seed=args.seed + rank))
     step, launches, profile_on, profile_read, e2e_io, status, keep = make_runner(
-        spec, inp, dev, args.tc_ksplit, args.tc_replicas)
+        spec, inp, dev, args.tc_ksplit)
     nsm = torch.cuda.get_device_properties(dev).multi_processor_count
     flush = torch.empty(int(2 * L2_BYTES // 4), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -871,13 +869,18 @@ def sample_plan(spec, inp, cores, budget_s):
     T0 = min(spec.T, 16)
     sp, ip = prefix(spec, inp, T0)
     per_step = oracle_sample(sp, ip, [0], 1) / T0
-    par = 1 if oracle_serial(spec) else cores
-    cap = spec.B if oracle_serial(spec) else cores
     per_row = per_step * spec.T
-    if per_row <= budget_s * par:
-        n = max(1, min(spec.B, cap, int(budget_s * par / max(per_row, 1e-9))))
-        return list(range(n)), spec.T
-    return [0], max(1, min(spec.T, int(budget_s / max(per_step, 1e-9))))
+    if oracle_serial(spec):
+        # rows one after another on one thread: as many whole rows as fit
+        if per_row <= budget_s:
+            return list(range(max(1, min(spec.B, int(budget_s / max(per_row, 1e-9)))))), spec.T
+        return [0], max(1, min(spec.T, int(budget_s / max(per_step, 1e-9))))
+    # one row per core, in parallel: all steps when a whole row fits the
+    # budget, else the longest prefix that does
+    rows = list(range(max(1, min(spec.B, cores))))
+    if per_row <= budget_s:
+        return rows, spec.T
+    return rows, max(1, min(spec.T, int(budget_s / max(per_step, 1e-9))))
 
 
 def cpu_baseline(spec, inp, budget_s=20.0):
@@ -999,8 +1002,6 @@ def main(argv=None):
                          "opt-in down-conversion to the tensor cores)")
     ap.add_argument("--tc-ksplit", type=int, default=0, choices=[0, 1, 2, 4],
                     help="tensor-core recurrence: CTAs splitting K (0 = the library's choice)")
-    ap.add_argument("--tc-replicas", type=int, default=0,
-                    help="tensor-core recurrence: step-counter replicas (0 = the library's)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -1027,7 +1028,7 @@ def main(argv=None):
         else:
             line["cpu_baseline"] = None
         if (ws == 1 and not args.no_configs and args.workload == "gru" and args.T == 0 and
-                not args.dtype and not args.tc_ksplit and not args.tc_replicas):
+                not args.dtype and not args.tc_ksplit):
             line["configs"] = run_configs(args, rank, local, ws)
         print(json.dumps(line), flush=True)
     if torch.distributed.is_initialized():

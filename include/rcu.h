@@ -94,10 +94,6 @@ typedef struct rcu_rssm_s *rcu_rssm_t;
                                          steps (layer l+1 on chunk c while layer l runs chunk
                                          c+1), on streams the handle owns; results equal the
                                          layer-by-layer ones.  0 = layer by layer */
-#define RCU_ATTR_TC_COUNTER_REPLICAS 9 /* tensor-core recurrent kernel: copies of each step
-                                         counter, each on its own 128-byte line; every CTA
-                                         adds to all of them and polls one (1 .. 16,
-                                         default 8) */
 #define RCU_ATTR_PROFILE 4            /* 1 = record a CUDA event pair around every kernel
                                          this handle launches (RSSM handle: around each
                                          named phase of launches), on the launching

@@ -28,7 +28,6 @@ RCU_OK, RCU_ERR_INVALID, RCU_ERR_UNSUPPORTED, RCU_ERR_CUDA = 0, -1, -2, -3
 RCU_ERR_TIMEOUT, RCU_ERR_LENGTHS, RCU_ERR_STATE = -4, -5, -6
 RCU_ATTR_BARRIER_TIMEOUT_NS, RCU_ATTR_TEST_DROP_ARRIVAL, RCU_ATTR_FORCE_PATH = 1, 2, 3
 RCU_ATTR_PROFILE, RCU_ATTR_TRACE, RCU_ATTR_TC_KSPLIT = 4, 5, 7
-RCU_ATTR_TC_COUNTER_REPLICAS = 9
 RCU_ATTR_LAYER_PIPELINE = 10
 RCU_CLIP_CELL, RCU_CLIP_PROJ = 0, 1
 RCU_ATTR_HOST_CHUNKS, RCU_MAX_HOST_CHUNKS = 8, 16

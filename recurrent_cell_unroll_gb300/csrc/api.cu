@@ -80,7 +80,6 @@ struct rcu_rnn_s : EventProfiler {
   int drop_arrival = 0;
   int force_path = 0;
   int tc_ksplit = 0;   // CTAs splitting K in the tensor-core recurrent kernel (0 = automatic)
-  int tc_replicas = 8;  // RCU_ATTR_TC_COUNTER_REPLICAS
   // LSTM clipping (rnn_set_clip)
   int cclip = 0, pclip = 0;
   float cclip_lo = 0.f, cclip_hi = 0.f, pclip_lo = 0.f, pclip_hi = 0.f;
@@ -251,11 +250,6 @@ extern "C" int rnn_set_attr(rcu_rnn_t h, int attr, int64_t value) {
     case RCU_ATTR_LAYER_PIPELINE:
       if (value != 0 && value != 1) return fail(RCU_ERR_INVALID, "layer pipeline must be 0 or 1");
       h->layer_pipeline = (int)value;
-      return RCU_OK;
-    case RCU_ATTR_TC_COUNTER_REPLICAS:
-      if (value < 1 || value > TC_MAX_COUNTER_REPLICAS)
-        return fail(RCU_ERR_INVALID, "counter replicas must be 1 .. %d", TC_MAX_COUNTER_REPLICAS);
-      h->tc_replicas = (int)value;
       return RCU_OK;
     case RCU_ATTR_FORCE_PATH:
       if (value < 0 || value > 3) return fail(RCU_ERR_INVALID, "force_path must be 0, 1, 2 or 3");
@@ -649,7 +643,6 @@ static int forward_layer_pipelined(rcu_rnn_t h, int T, int B, const void *X0, in
       TcRecParams tp;
       tp.base = pf;
       tp.ksplit = h->tc_ksplit;
-      tp.counter_replicas = h->tc_replicas;
       tp.Wtc[0] = tp.Wtc[1] = h->lw[l].fold_w.p;
       h->begin("recurrent_tc_lstmp", sl);
       cudaError_t e = launch_tc_recurrent(tp, h->nsm, sl);
@@ -848,7 +841,6 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
       TcRecParams tp;
       tp.base = pf;
       tp.ksplit = h->tc_ksplit;
-      tp.counter_replicas = h->tc_replicas;
       for (int d = 0; d < D; ++d) tp.Wtc[d] = h->lw[(size_t)l * D + d].fold_w.p;
       h->begin("recurrent_tc_lstmp", s);
       cudaError_t e = launch_tc_recurrent(tp, h->nsm, s);
@@ -900,7 +892,6 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
       TcRecParams tp;
       tp.base = p;
       tp.ksplit = h->tc_ksplit;
-      tp.counter_replicas = h->tc_replicas;
       for (int d = 0; d < D; ++d) tp.Wtc[d] = h->lw[(size_t)l * D + d].tc_whh.p;
       cudaError_t e = launch_tc_recurrent(tp, h->nsm, s);
       if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "tc recurrent: %s", cudaGetErrorString(e));

@@ -44,7 +44,6 @@ constexpr int MAX_STAGES = 8;
 struct Maps {
   CUtensorMap hx;    // [D*2*B rows][K cols], ld Kp, bf16, box 64 x a_rows
   CUtensorMap w[2];  // per direction [NU16*nG*16 rows][K cols], ld Kp, bf16, box 64 x N
-  int reps;          // replicas of each step counter (1 .. TC_MAX_COUNTER_REPLICAS)
   // h rows loaded per stage: 128, or round_up(B, 8) when one batch group
   // holds the whole batch (the stage's other rows are never read back: a
   // row of D depends only on the same row of A, and the epilogue skips rows
@@ -163,13 +162,8 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
   // that ordering is what lets the partial-sum buffer be reused step after
   // step and bounds the sends in flight to one step.  (Waiting only for the
   // producers of a CTA's own K share would break it.)
-  // The counter is replicated maps.reps times, each replica on its own
-  // 128-byte line: every CTA adds to every replica (one lane per replica) and
-  // polls one of them, so no line has more than NU / reps pollers.  (With all
-  // NU CTAs polling one line, the last arrival took up to 2.8 us to reach
-  // every poller.)
-  unsigned *ctr_rep = p.ctr + (size_t)(d * NBG + bg) * (TC_MAX_COUNTER_REPLICAS * 32) + 16;
-  unsigned *ctr = ctr_rep + (size_t)(cu % maps.reps) * 32;  // the replica this CTA polls
+  // (each counter on its own 128-byte line, away from the error word)
+  unsigned *ctr = p.ctr + (size_t)(d * NBG + bg) * 32 + 16;
   const unsigned n_wait = (unsigned)NU;
   // steps this batch group runs: the longest row of the group (rows sorted by length)
   const int Tg = row0 < B ? p.meta.lens_sorted[row0] : 0;
@@ -366,10 +360,7 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
     }
     fence_proxy_async_global();
     epi_bar();
-    if (threadIdx.x >= 64 && threadIdx.x < 64 + maps.reps) {
-      red_release_gpu_add(ctr_rep + (size_t)(threadIdx.x - 64) * 32,
-                          (p.drop_arrival && blockIdx.x == 0) ? 0u : 1u);
-    }
+    if (threadIdx.x == 64) red_release_gpu_add(ctr, (p.drop_arrival && blockIdx.x == 0) ? 0u : 1u);
     // the input projection G of step st for this thread's row and units
     // (loaded a whole step ahead of its use: right after the previous step's
     // gates, so its latency is off the critical path)
@@ -476,7 +467,6 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
         }
       }
       if (p.trace && threadIdx.x == 64) stamp(p, step, 13, globaltimer_ns());
-      load_g(step + 1);
       // exchange buffer for the next step (bf16 MMA operand): on the critical path
       if (active) {
         __nv_bfloat16 *dst = hx + (size_t)(((step & 1) ^ 1) * B + s) * Kp + ub;
@@ -496,13 +486,17 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
       if (p.trace && threadIdx.x == 64) stamp(p, step, 6, globaltimer_ns());
       fence_proxy_async_global();
       epi_bar();
-      if (threadIdx.x >= 64 && threadIdx.x < 64 + maps.reps) {
-        if (p.trace && threadIdx.x == 64) stamp(p, step, 7, globaltimer_ns());
+      if (threadIdx.x == 64) {
+        if (p.trace) stamp(p, step, 7, globaltimer_ns());
         // release: orders the epilogue's h_t stores (all threads, through the
-        // barrier above) before the arrival on replica threadIdx.x - 64
-        red_release_gpu_add(ctr_rep + (size_t)(threadIdx.x - 64) * 32, 1u);
-        if (p.trace && threadIdx.x == 64) stamp(p, step, 4, globaltimer_ns());
+        // barrier above) before the arrival
+        red_release_gpu_add(ctr, 1u);
+        if (p.trace) stamp(p, step, 4, globaltimer_ns());
       }
+      // the next step's G: loaded after the release (a release waits for the
+      // thread's earlier loads too, and the address needs the step offset
+      // table, whose load the h_t store would otherwise wait behind)
+      load_g(step + 1);
       // outputs leave the critical path: written after h_t is published
       if (active && p.y) {
         float *yo = p.y + ((size_t)tt * B + b) * ldo + (size_t)d * p.Hout + ub;
@@ -639,7 +633,7 @@ bool tc_rec_supported(int cell, int H, int Hout, int P, int nsm, int B, int D) {
 }
 
 int tc_rec_counters(int B, int D) {
-  return D * ceil_div(B, BG) * TC_MAX_COUNTER_REPLICAS * 32 + 32;
+  return D * ceil_div(B, BG) * 32 + 32;
 }
 
 namespace {
@@ -721,7 +715,7 @@ cudaError_t launch_tc_recurrent(const TcRecParams &tp, int nsm, cudaStream_t s) 
   maps.a_rows = NBG == 1 ? round_up(p.B, 8) : BG;
   if (!make_map(&maps.hx, p.hx, (long long)p.D * 2 * p.B, p.Hout, p.Kp, maps.a_rows))
     return cudaErrorInvalidValue;
-  maps.reps = std::min(std::max(tp.counter_replicas, 1), TC_MAX_COUNTER_REPLICAS);
+
 
   // K split over ks CTAs (a cluster): requested (1, 2 or 4), or automatic (a
   // pair); halved until the plan fits shared memory and gives every CTA a K block

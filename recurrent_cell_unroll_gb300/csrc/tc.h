@@ -18,22 +18,18 @@ cudaError_t launch_tc_gemm(const __nv_bfloat16 *X, int ldx, const __nv_bfloat16 
                            const float *bias, float *G, int ldg, int M, const int32_t *M_dev,
                            int N, int K, int nsm, cudaStream_t s, int *err, uint64_t timeout_ns);
 
-// most replicas of a step counter (RCU_ATTR_TC_COUNTER_REPLICAS)
-constexpr int TC_MAX_COUNTER_REPLICAS = 16;
-
 // ---- recurrent_tc.cu: persistent recurrent kernel with the per-step
 // h W_hh^T on tcgen05.
 struct TcRecParams {
   RecParams base;
   const void *Wtc[2];  // tensor-core packed W_hh per direction (tc_pack_whh)
   int ksplit = 0;      // CTAs splitting K: 0 = automatic (2), 1 = none, 2 or 4 = a cluster
-  int counter_replicas = 8;  // replicas of each step counter (RCU_ATTR_TC_COUNTER_REPLICAS)
 };
 // weights can be packed for the tensor-core kernel (shape only)
 bool tc_rec_packable(int cell, int H, int Hout, int P);
 // the kernel can run this forward (co-resident grid for B rows, D directions)
 bool tc_rec_supported(int cell, int H, int Hout, int P, int nsm, int B, int D);
-// barrier counter words one layer needs (each replica on its own 128-byte line)
+// barrier counter words one layer needs (each counter on its own 128-byte line)
 int tc_rec_counters(int B, int D);
 // CTAs of the kernel's first-choice plan (K split as requested or automatic)
 int tc_rec_grid(int cell, int H, int Hout, int B, int D, int ksplit);

@@ -5,7 +5,7 @@ Runs one workload a few times, then once with the library's step trace on
 CTA 0, resolution about 256 ns) and prints the median time between stamps.
 
     python -m recurrent_cell_unroll_gb300.step_trace --workload gru --T 64 [--ksplit 1]
-        [--replicas N] [--all-ctas]
+        [--all-ctas]
 
 --all-ctas (tensor-core recurrence): every CTA's stamps for steps 16..23, to
 see how far apart the CTAs publish h_t and how long the last publication
@@ -92,8 +92,7 @@ def all_cta_summary(rows: np.ndarray):
     return out
 
 
-def run(workload: str, T: int = 0, ksplit: int = 0, seed: int = 0, replicas: int = 0,
-        all_ctas: bool = False):
+def run(workload: str, T: int = 0, ksplit: int = 0, seed: int = 0, all_ctas: bool = False):
     spec = WORKLOADS[workload]
     if T > 0:
         kw = {"T": T}
@@ -123,8 +122,6 @@ def run(workload: str, T: int = 0, ksplit: int = 0, seed: int = 0, replicas: int
         net = binding.RNN.from_spec(spec)
         if ksplit:
             net.set_attr(binding.RCU_ATTR_TC_KSPLIT, ksplit)
-        if replicas:
-            net.set_attr(binding.RCU_ATTR_TC_COUNTER_REPLICAS, replicas)
         net.set_weights(inp["weights"])
         x = inp["x"].to(dev)
         h0 = inp["h0"].to(dev) if inp["h0"] is not None else None
@@ -164,11 +161,10 @@ def main(argv=None):
     ap.add_argument("--workload", default="gru", choices=sorted(WORKLOADS))
     ap.add_argument("--T", type=int, default=64, help="sequence length (0 = the workload's)")
     ap.add_argument("--ksplit", type=int, default=0, choices=[0, 1, 2, 4])
-    ap.add_argument("--replicas", type=int, default=0, help="step-counter replicas (0 = default)")
     ap.add_argument("--all-ctas", action="store_true",
                     help="also every CTA's stamps for steps 16..23 (tensor-core kernel)")
     args = ap.parse_args(argv)
-    r = run(args.workload, args.T, args.ksplit, replicas=args.replicas, all_ctas=args.all_ctas)
+    r = run(args.workload, args.T, args.ksplit, all_ctas=args.all_ctas)
     print(f"{r['workload']} T={r['T']} kernel={r['kernel']} "
           f"step period (median) {r['step_period_ns']:.0f} ns")
     for label, v in r["phases_ns"]:

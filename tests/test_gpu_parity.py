@@ -240,17 +240,15 @@ KSPLIT = [
 
 @pytest.mark.parametrize("spec", KSPLIT, ids=lambda s: f"{s.name}-T{s.T}-B{s.B}-H{s.hidden}")
 @pytest.mark.parametrize("ksplit", [1, 2, 4])
-@pytest.mark.parametrize("replicas", [1, 8, 16])
-def test_tensor_core_k_split(spec, ksplit, replicas):
+def test_tensor_core_k_split(spec, ksplit):
     """h W_hh^T with K kept whole (1) or split over a CTA pair (2) or four
     CTAs (4) whose partial sums are exchanged through distributed shared
-    memory; each step counter kept once or replicated 8 or 16 times."""
+    memory."""
     inp = wl.make_rnn_inputs(spec, seed=17)
     dev = torch.device("cuda")
     net = binding.RNN.from_spec(spec)
     net.set_attr(binding.RCU_ATTR_FORCE_PATH, 2)
     net.set_attr(binding.RCU_ATTR_TC_KSPLIT, ksplit)
-    net.set_attr(binding.RCU_ATTR_TC_COUNTER_REPLICAS, replicas)
     net.set_attr(binding.RCU_ATTR_PROFILE, 1)
     net.set_weights(inp["weights"])
     lengths = inp["lengths"].to(dev) if inp["lengths"] is not None else None
