@@ -78,7 +78,10 @@ typedef struct rcu_rssm_s *rcu_rssm_t;
 #define RCU_ATTR_FORCE_PATH 3         /* 0 = automatic, 1 = portable SIMT kernels only,
                                          2 = tensor-core (tcgen05) kernels where supported,
                                          3 = cluster-resident recurrent kernel where W_hh
-                                         fits one thread-block cluster (else SIMT) */
+                                         fits one thread-block cluster (else SIMT).  On an
+                                         RSSM handle: 0 = automatic, 1 = the backward's
+                                         reverse-time chain as separate launches per step
+                                         instead of one cluster-resident kernel */
 #define RCU_ATTR_TRACE 5              /* 1 = record per-step timestamps (rnn_get_trace);
                                          2 = also every CTA's stamps of the tensor-core
                                          recurrence for a window of steps */

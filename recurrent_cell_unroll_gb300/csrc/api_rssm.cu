@@ -27,6 +27,7 @@ struct rcu_rssm_s : EventProfiler {
   DevBuf ctl;  // device error word
   int64_t timeout_ns = 2000000000LL;  // bound on each wait for a broadcast vector
   int drop_send = 0;                  // testing: RCU_ATTR_TEST_DROP_ARRIVAL
+  int force_path = 0;                 // RCU_ATTR_FORCE_PATH: 1 = backward chain as separate launches
   bool trace = false;
   DevBuf trace_buf;
   int trace_T = 0;
@@ -54,6 +55,11 @@ extern "C" int rssm_set_attr(rcu_rssm_t h, int attr, int64_t value) {
   }
   if (attr == RCU_ATTR_PROFILE) {
     h->profile = value != 0;
+    return RCU_OK;
+  }
+  if (attr == RCU_ATTR_FORCE_PATH) {
+    if (value != 0 && value != 1) return fail(RCU_ERR_INVALID, "RSSM force_path must be 0 or 1");
+    h->force_path = (int)value;
     return RCU_OK;
   }
   if (attr != RCU_ATTR_TRACE) return fail(RCU_ERR_INVALID, "rssm_set_attr: unknown attribute %d", attr);
@@ -373,21 +379,43 @@ static int rssm_backward_run(rcu_rssm_t h, bool with_actor, int T, int B, const 
   if (e == cudaSuccess) e = launch_elu(V, Q, (size_t)M * Hd, s);  // q = ELU(v)
   ++launches;
   gemm(Q, Hd, W3, Hd, b3, Pm, S2, M, S2, Hd);                    // p = W3 q + b3
+  // the given-actions chain runs as one cluster kernel with the weights
+  // resident (it reads them untransposed) when they fit; otherwise, and with
+  // the actor, as batched mat-vecs between elementwise kernels
+  const bool fused = !with_actor && h->force_path != 1 && rssm_bwd_chain_supported(S, A, Hd, RH);
   // transposed weights for the chain's mat-vecs (X W^T form of the GEMM)
-  tr(W3, S2, Hd, Hd, W3T, S2);
-  tr(W2, Hd, RH, RH, W2T, Hd);
-  tr(Whh, G, RH, RH, WhhT, G);
-  tr(Wih, G, Hd, Hd, WihT, G);
-  tr(W1, Hd, S, SA, W1sT, Hd);
+  if (!fused) {
+    tr(W3, S2, Hd, Hd, W3T, S2);
+    tr(W2, Hd, RH, RH, W2T, Hd);
+    tr(Whh, G, RH, RH, WhhT, G);
+    tr(Wih, G, Hd, Hd, WihT, G);
+    tr(W1, Hd, S, SA, W1sT, Hd);
+  }
   if (A > 0) tr(W1 + S, Hd, A, SA, W1aT, Hd);
   h->end(s);
   if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rssm_backward: recompute: %s", cudaGetErrorString(e));
   // ---- the reverse-time chain (one timed span over all its launches)
   h->begin("rssm_bwd_chain", s);
-  CU(cudaMemsetAsync(GH, 0, (size_t)B * RH * 4, s));
-  CU(cudaMemsetAsync(DHZ, 0, (size_t)B * RH * 4, s));
-  CU(cudaMemsetAsync(CS, 0, (size_t)B * S * 4, s));
-  for (int t = T - 1; t >= 0 && e == cudaSuccess; --t) {
+  if (fused) {
+    RssmBwdChainParams cp{};
+    cp.S = S; cp.A = A; cp.Hd = Hd; cp.RH = RH; cp.T = T; cp.B = B;
+    cp.W1 = W1; cp.Wih = Wih; cp.Whh = Whh; cp.W2 = W2; cp.W3 = W3;
+    cp.dmeans = dmeans; cp.dstds = dstds; cp.dstates = dstates; cp.dbeliefs = dbeliefs;
+    cp.eps = eps; cp.p = Pm; cp.v = V; cp.u = U; cp.gates = ZI; cp.zh = ZH; cp.hp = HP;
+    cp.DP = DP; cp.DV = DV; cp.DA = DA; cp.DR = DR; cp.DU = DU;
+    cp.cs_out = CS;  // ds_{-1}
+    cp.gh_out = GH;  // dh_{-1}, the W_hh^T dR_0 and z_0 dh_0 parts together
+    cp.err = err;
+    cp.timeout_ns = (uint64_t)h->timeout_ns;
+    e = launch_rssm_bwd_chain(cp, h->nsm, s);
+    ++launches;
+    CU(cudaMemsetAsync(DHZ, 0, (size_t)B * RH * 4, s));  // already in GH
+  } else {
+    CU(cudaMemsetAsync(GH, 0, (size_t)B * RH * 4, s));
+    CU(cudaMemsetAsync(DHZ, 0, (size_t)B * RH * 4, s));
+    CU(cudaMemsetAsync(CS, 0, (size_t)B * S * 4, s));
+  }
+  for (int t = T - 1; !fused && t >= 0 && e == cudaSuccess; --t) {
     const size_t r0 = (size_t)t * B;
     e = launch_rssm_sample_grad(t, B, S, dmeans, dstds, dstates, eps, Pm, CS, DP, s);
     ++launches;

@@ -128,6 +128,29 @@ struct RssmParams {
   float *actions_out;
 };
 cudaError_t launch_rssm(const RssmParams &p, int nsm, cudaStream_t s, int *clusters_used);
+
+// Reverse-time chain of the RSSM backward pass (given actions) in one launch:
+// per step ds_t -> dp -> dv -> dh_t -> gate gradients -> du -> ds_{t-1} and
+// dh_{t-1}, the transposed weights resident in a thread-block cluster.
+struct RssmBwdChainParams {
+  int S, A, Hd, RH, T, B;
+  const float *W1, *Wih, *Whh, *W2, *W3;              // PyTorch layout, fp32
+  const float *dmeans, *dstds, *dstates, *dbeliefs;   // [T][B][S] / [T][B][RH], NULL = 0
+  const float *eps;                                   // [T][B][S]
+  const float *p;                                     // head outputs [T*B][2S]
+  const float *v, *u;                                 // pre-ELU W2 h + b2, W1 [s, a] + b1 [T*B][Hd]
+  const float *gates;                                 // activated r, z, n [T*B][3RH]
+  const float *zh;                                    // hidden-side pre-activations [T*B][3RH]
+  const float *hp;                                    // h_{t-1} [T*B][RH]
+  float *DP, *DV, *DA, *DR, *DU;                      // [T*B][2S], [Hd], [3RH], [3RH], [Hd]
+  float *cs_out;                                      // [B][S]: ds_{-1} (dstate0)
+  float *gh_out;                                      // [B][RH]: dh_{-1} (dbelief0)
+  int *err;
+  uint64_t timeout_ns;
+};
+// false (nothing launched) when the resident plan does not fit
+bool rssm_bwd_chain_supported(int S, int A, int Hd, int RH);
+cudaError_t launch_rssm_bwd_chain(const RssmBwdChainParams &p, int nsm, cudaStream_t s);
 // the weights (and, with Hx > 0, the actor's) fit one cluster's shared memory
 bool rssm_supported(int S, int A, int Hd, int RH, int Hx = 0);
 

@@ -531,6 +531,297 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Reverse-time chain of the backward pass through the unroll (given
+// actions), the training use of the prior behind the same page.  Per step t,
+// from T-1 down to 0, for each row:
+//   ds = dstates_t + ds_t(from t+1),  dmean = dmeans_t + ds,
+//   dstd = dstds_t + ds * eps_t,  dp = [dmean, dstd * sigmoid(p_std)];
+//   dv = (W3^T dp) * ELU'(v);
+//   dh = dbeliefs_t + W2^T dv + W_hh^T dR_{t+1} + z_{t+1} * dh_{t+1};
+//   GRU gate gradients dA (input side) and dR (hidden side) from r, z, n,
+//   the hidden-side n pre-activation and h_{t-1};
+//   du = (W_ih^T dA) * ELU'(u);  ds_{t-1} = W1[:, :S]^T du.
+// Everything off this chain (the forward's activations, the weight and
+// action gradients) is GEMMs over all rows outside the kernel.  As in the
+// forward kernel, a cluster of RC CTAs holds the weights (here transposed for
+// W^T x, each CTA the columns of the outputs it owns, and every CTA all of
+// W1's state columns), the rows of one batch slice run through four phases
+// per step, and the three vectors every CTA needs in full (dv, dR with dA,
+// du) are broadcast with st.async into every CTA's shared memory, each
+// counted on that vector's mbarrier.  A CTA sends a vector of step t-1 only
+// after every CTA has sent du of step t, which each does after reading all
+// three vectors of step t, so one buffer per vector suffices.
+constexpr int MAXBC_BWD = 4;
+
+struct BwdDims {
+  int S, Hd, RH, Bc, Ha, Ua, Hap, Uap, Sp, S2p, Hdp, G3p;
+};
+__host__ __device__ inline BwdDims make_bdims(int S, int Hd, int RH, int Bc) {
+  BwdDims d;
+  d.S = S; d.Hd = Hd; d.RH = RH; d.Bc = Bc;
+  d.Ha = ceil_div(Hd, RC);
+  d.Ua = ceil_div(RH, RC);
+  d.Hap = r4(d.Ha);
+  d.Uap = r4(d.Ua);
+  d.Sp = r4(S);
+  d.S2p = r4(2 * S);
+  d.Hdp = r4(Hd);
+  d.G3p = r4(3 * RH);
+  return d;
+}
+struct BwdLayout {
+  size_t w3, w2, whh, wih, w1s;       // weights, [k][o]
+  size_t dp, dv, dra, du, cs, gh, dhz;  // vectors, [Bc][padded width]
+  size_t part1, part2, total;
+};
+__host__ __device__ inline BwdLayout make_blayout(const BwdDims &d) {
+  BwdLayout L;
+  size_t o = 0;
+  auto take = [&](size_t n) { size_t r = o; o += (n + 3) & ~size_t(3); return r; };
+  L.w3 = take((size_t)2 * d.S * d.Hap);    // W3^T dp -> owned outputs of Hd
+  L.w2 = take((size_t)d.Hd * d.Uap);       // W2^T dv -> owned units
+  L.whh = take((size_t)3 * d.RH * d.Uap);  // W_hh^T dR -> owned units
+  L.wih = take((size_t)3 * d.RH * d.Hap);  // W_ih^T dA -> owned outputs of Hd
+  L.w1s = take((size_t)d.Hd * d.Sp);       // W1[:, :S]^T du -> every state entry
+  L.dp = take((size_t)d.Bc * d.S2p);
+  L.dv = take((size_t)d.Bc * d.Hdp);
+  L.dra = take((size_t)d.Bc * 2 * d.G3p);  // per row: dR [3RH], then dA [3RH]
+  L.du = take((size_t)d.Bc * d.Hdp);
+  L.cs = take((size_t)d.Bc * d.Sp);
+  L.gh = take((size_t)d.Bc * d.Uap);
+  L.dhz = take((size_t)d.Bc * d.Uap);
+  int wmax = d.Hap > d.Uap ? d.Hap : d.Uap;
+  if (d.Sp > wmax) wmax = d.Sp;
+  L.part1 = take((size_t)KS_MAX * d.Bc * wmax);
+  L.part2 = take((size_t)KS_MAX * d.Bc * wmax);
+  L.total = o;
+  return L;
+}
+
+// dst[k * ldt + o] = src[k * ld + col0 + o] for k < K, o < n; zero for o in
+// [n, ncols) (a column slice of a row-major matrix, kept [k][o])
+__device__ __forceinline__ void load_cols(const float *src, int ld, int K, int col0, int n,
+                                          int ncols, int ldt, float *dst) {
+  for (int e = threadIdx.x; e < ncols * K; e += NT) {
+    const int k = e / ncols, o = e % ncols;
+    dst[(size_t)k * ldt + o] = o < n ? src[(size_t)k * ld + col0 + o] : 0.f;
+  }
+}
+
+enum BVec { BV_DV = 0, BV_DRA, BV_DU, NBVEC };
+
+template <int NR>
+__global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
+    rssm_bwd_chain_kernel(const RssmBwdChainParams p, int Bc) {
+  extern __shared__ __align__(16) float sm[];
+  cg::cluster_group cluster = cg::this_cluster();
+  const int c = (int)cluster.block_rank();
+  const int b0 = (int)(blockIdx.x / RC) * Bc;
+  const int nr = min(Bc, p.B - b0);  // rows of this cluster (uniform across the cluster)
+  const BwdDims d = make_bdims(p.S, p.Hd, p.RH, Bc);
+  const BwdLayout L = make_blayout(d);
+  const int S = d.S, Hd = d.Hd, RH = d.RH, G = 3 * RH, S2 = 2 * S;
+  const int i0 = c * d.Ha, ni = max(0, min(d.Ha, Hd - i0));  // owned outputs of Hd
+  const int j0 = c * d.Ua, nj = max(0, min(d.Ua, RH - j0));  // owned GRU units
+  const int tid = threadIdx.x;
+  const int ldra = 2 * d.G3p;
+
+  for (size_t e = tid; e < L.total; e += NT) sm[e] = 0.f;
+  __syncthreads();
+  load_cols(p.W3, Hd, S2, i0, ni, d.Ha, d.Hap, sm + L.w3);
+  load_cols(p.W2, RH, Hd, j0, nj, d.Ua, d.Uap, sm + L.w2);
+  load_cols(p.Whh, RH, G, j0, nj, d.Ua, d.Uap, sm + L.whh);
+  load_cols(p.Wih, Hd, G, i0, ni, d.Ha, d.Hap, sm + L.wih);
+  load_cols(p.W1, S + p.A, Hd, 0, S, S, d.Sp, sm + L.w1s);
+  __shared__ uint64_t vbar[NBVEC];
+  __shared__ int s_ok;
+  if (tid == 0) {
+    for (int v = 0; v < NBVEC; ++v) tc::mbar_init(&vbar[v], 1);
+    tc::fence_mbar_init();
+  }
+  // every CTA's buffers are zero and its mbarriers exist before any peer sends
+  cluster.sync();
+
+  const uint32_t sm0 = (uint32_t)__cvta_generic_to_shared(sm);
+  uint32_t rsm[RC], rbar[RC];
+#pragma unroll
+  for (int r = 0; r < RC; ++r) {
+    rsm[r] = tc::mapa_shared(sm0, (uint32_t)r);
+    rbar[r] = tc::mapa_shared((uint32_t)__cvta_generic_to_shared(&vbar[0]), (uint32_t)r);
+  }
+  auto bcast = [&](size_t off, float v, int vec) {
+#pragma unroll
+    for (int r = 0; r < RC; ++r)
+      st_async_b32(rsm[r] + (uint32_t)(off * 4), v, rbar[r] + (uint32_t)(vec * 8));
+  };
+  uint32_t vbytes[NBVEC];
+  vbytes[BV_DV] = (uint32_t)(Bc * Hd * 4);
+  vbytes[BV_DRA] = (uint32_t)(Bc * 2 * G * 4);
+  vbytes[BV_DU] = (uint32_t)(Bc * Hd * 4);
+  uint32_t uses = 0;  // thread 0: completed uses per vector, 4 bits each
+  volatile int abort_ = 0;
+  const uint64_t tmo = p.timeout_ns;
+  auto wait_vec = [&](int vec) -> bool {
+    if (tid == 0) {
+      const uint32_t n = (uses >> (4 * vec)) & 15u;
+      tc::mbar_arrive_expect_tx(&vbar[vec], vbytes[vec]);
+      s_ok = tc::mbar_wait(&vbar[vec], n & 1u, p.err, &abort_, tmo);
+      uses = (uses & ~(15u << (4 * vec))) | (((n + 1) & 15u) << (4 * vec));
+    }
+    __syncthreads();
+    return s_ok != 0;
+  };
+  const int ks_a = split_of(d.Hap, S2), ks_b = split_of(d.Uap, Hd);
+  const int ks_c = split_of(d.Uap, G), ks_d = split_of(d.Hap, G), ks_e = split_of(d.Sp, Hd);
+  float *part1 = sm + L.part1, *part2 = sm + L.part2;
+  bool ok = true;
+
+  for (int t = p.T - 1; t >= 0; --t) {
+    const size_t rt = (size_t)t * p.B + b0;  // packed row of (t, b0)
+    // ---- phase 1: dp of the sample and head (every CTA, all of its rows),
+    //      dv = (W3^T dp) * ELU'(v) for the owned outputs, broadcast
+    for (int e = tid; e < Bc * S; e += NT) {
+      const int r = e / S, j = e % S;
+      float dm = 0.f, dsd = 0.f;
+      if (r < nr) {
+        const size_t o = (rt + r) * S + j;
+        const float ds = (p.dstates ? p.dstates[o] : 0.f) + sm[L.cs + (size_t)r * d.Sp + j];
+        dm = (p.dmeans ? p.dmeans[o] : 0.f) + ds;
+        dsd = ((p.dstds ? p.dstds[o] : 0.f) + ds * p.eps[o]) *
+              sigmoid_f(p.p[(rt + r) * S2 + S + j]);
+        if (c == 0) {
+          p.DP[(rt + r) * S2 + j] = dm;
+          p.DP[(rt + r) * S2 + S + j] = dsd;
+        }
+      }
+      sm[L.dp + (size_t)r * d.S2p + j] = dm;
+      sm[L.dp + (size_t)r * d.S2p + S + j] = dsd;
+    }
+    __syncthreads();
+    matvec_part<NR>(sm + L.w3, d.Hap, S2, sm + L.dp, d.S2p, ks_a, part1);
+    __syncthreads();
+    reduce_parts(part1, d.Hap, Bc, ks_a);
+    __syncthreads();
+    for (int e = tid; e < ni * Bc; e += NT) {
+      const int o = e % ni, r = e / ni;
+      float dv = 0.f;
+      if (r < nr) {
+        const float vv = p.v[(rt + r) * Hd + i0 + o];
+        dv = part_sum(part1, d.Hap, r, o) * (vv > 0.f ? 1.f : expf(vv));
+        p.DV[(rt + r) * Hd + i0 + o] = dv;
+      }
+      bcast(L.dv + (size_t)r * d.Hdp + i0 + o, dv, BV_DV);
+    }
+    if (!(ok = wait_vec(BV_DV))) break;
+    // ---- phase 2: dh of the owned units, their gate gradients; dR and dA broadcast
+    matvec_part<NR>(sm + L.w2, d.Uap, Hd, sm + L.dv, d.Hdp, ks_b, part1);
+    __syncthreads();
+    reduce_parts(part1, d.Uap, Bc, ks_b);
+    __syncthreads();
+    for (int e = tid; e < nj * Bc; e += NT) {
+      const int jj = e % nj, r = e / nj, j = j0 + jj;
+      float ar = 0.f, az = 0.f, dan = 0.f, rg = 0.f;
+      if (r < nr) {
+        const size_t row = rt + r;
+        const float dh = (p.dbeliefs ? p.dbeliefs[row * RH + j] : 0.f) +
+                         part_sum(part1, d.Uap, r, jj) + sm[L.gh + (size_t)r * d.Uap + jj] +
+                         sm[L.dhz + (size_t)r * d.Uap + jj];
+        const float *g = p.gates + row * G;
+        rg = g[j];
+        const float z = g[RH + j], n = g[2 * RH + j];
+        const float hn = p.zh[row * G + 2 * RH + j];
+        const float dn = dh * (1.f - z), dz = dh * (p.hp[row * RH + j] - n);
+        dan = dn * (1.f - n * n);
+        ar = dan * hn * rg * (1.f - rg);
+        az = dz * z * (1.f - z);
+        float *da = p.DA + row * G, *dr = p.DR + row * G;
+        da[j] = ar; da[RH + j] = az; da[2 * RH + j] = dan;
+        dr[j] = ar; dr[RH + j] = az; dr[2 * RH + j] = dan * rg;
+        sm[L.dhz + (size_t)r * d.Uap + jj] = dh * z;
+      }
+      const size_t rb = L.dra + (size_t)r * ldra;
+      bcast(rb + j, ar, BV_DRA);
+      bcast(rb + RH + j, az, BV_DRA);
+      bcast(rb + 2 * RH + j, dan * rg, BV_DRA);
+      bcast(rb + d.G3p + j, ar, BV_DRA);
+      bcast(rb + d.G3p + RH + j, az, BV_DRA);
+      bcast(rb + d.G3p + 2 * RH + j, dan, BV_DRA);
+    }
+    if (!(ok = wait_vec(BV_DRA))) break;
+    // ---- phase 3: W_hh^T dR for the owned units (carried to step t-1),
+    //      du = (W_ih^T dA) * ELU'(u) for the owned outputs, broadcast
+    matvec_part<NR>(sm + L.whh, d.Uap, G, sm + L.dra, ldra, ks_c, part1);
+    matvec_part<NR>(sm + L.wih, d.Hap, G, sm + L.dra + d.G3p, ldra, ks_d, part2);
+    __syncthreads();
+    reduce_parts(part1, d.Uap, Bc, ks_c);
+    reduce_parts(part2, d.Hap, Bc, ks_d);
+    __syncthreads();
+    for (int e = tid; e < nj * Bc; e += NT) {
+      const int jj = e % nj, r = e / nj;
+      sm[L.gh + (size_t)r * d.Uap + jj] = part_sum(part1, d.Uap, r, jj);
+    }
+    for (int e = tid; e < ni * Bc; e += NT) {
+      const int o = e % ni, r = e / ni;
+      float du = 0.f;
+      if (r < nr) {
+        const float uu = p.u[(rt + r) * Hd + i0 + o];
+        du = part_sum(part2, d.Hap, r, o) * (uu > 0.f ? 1.f : expf(uu));
+        p.DU[(rt + r) * Hd + i0 + o] = du;
+      }
+      bcast(L.du + (size_t)r * d.Hdp + i0 + o, du, BV_DU);
+    }
+    if (!(ok = wait_vec(BV_DU))) break;
+    // ---- phase 4: ds_{t-1} = W1[:, :S]^T du (every CTA, every state entry)
+    matvec_part<NR>(sm + L.w1s, d.Sp, Hd, sm + L.du, d.Hdp, ks_e, part1);
+    __syncthreads();
+    reduce_parts(part1, d.Sp, Bc, ks_e);
+    __syncthreads();
+    for (int e = tid; e < Bc * S; e += NT) {
+      const int r = e / S, k = e % S;
+      sm[L.cs + (size_t)r * d.Sp + k] = part_sum(part1, d.Sp, r, k);
+    }
+    __syncthreads();
+  }
+  if (ok) {
+    // gradients reaching the initial state and belief
+    for (int e = tid; e < nr * S; e += NT) {
+      const int r = e / S, k = e % S;
+      if (c == 0 && p.cs_out) p.cs_out[(size_t)(b0 + r) * S + k] = sm[L.cs + (size_t)r * d.Sp + k];
+    }
+    for (int e = tid; e < nr * nj; e += NT) {
+      const int r = e / nj, jj = e % nj;
+      if (p.gh_out)
+        p.gh_out[(size_t)(b0 + r) * RH + j0 + jj] =
+            sm[L.gh + (size_t)r * d.Uap + jj] + sm[L.dhz + (size_t)r * d.Uap + jj];
+    }
+  }
+  // exit as the forward kernel: on a normal exit every byte sent here has
+  // been waited for; after a failed wait the cluster meets and each CTA lets
+  // stores already issued land before its shared memory goes away
+  if (!ok && tid == 0) atomicCAS(p.err, DEV_OK, DEV_TIMEOUT);
+  cluster.sync();
+  if (!ok || ld_volatile_int(p.err) != DEV_OK) {
+    const uint64_t until = globaltimer_ns() + 20000;  // 20 us
+    while (globaltimer_ns() < until) {
+    }
+  }
+}
+
+size_t bwd_smem_bytes(int S, int Hd, int RH, int Bc) {
+  return make_blayout(make_bdims(S, Hd, RH, Bc)).total * sizeof(float);
+}
+
+template <int NR>
+cudaError_t launch_bwd_nr(const RssmBwdChainParams &p, int Bc, int grid, size_t smem,
+                          cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute((const void *)rssm_bwd_chain_kernel<NR>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  rssm_bwd_chain_kernel<NR><<<grid, NT, smem, s>>>(p, Bc);
+  return cudaGetLastError();
+}
+
 int pick_bc(int B, int nsm) {
   int clusters = nsm / RC;
   if (clusters < 1) clusters = 1;
@@ -596,6 +887,25 @@ int resident_clusters(size_t smem, int Bc, int nsm) {
     return std::max(1, nsm / RC);
   }
   return n;
+}
+
+bool rssm_bwd_chain_supported(int S, int A, int Hd, int RH) {
+  if (S < 1 || A < 0 || Hd < 1 || RH < 1) return false;
+  return bwd_smem_bytes(S, Hd, RH, 1) <= SMEM_CAP;
+}
+
+cudaError_t launch_rssm_bwd_chain(const RssmBwdChainParams &p, int nsm, cudaStream_t s) {
+  int Bc = std::min(pick_bc(p.B, nsm), MAXBC_BWD);
+  while (Bc > 1 && bwd_smem_bytes(p.S, p.Hd, p.RH, Bc) > SMEM_CAP) --Bc;
+  const size_t smem = bwd_smem_bytes(p.S, p.Hd, p.RH, Bc);
+  if (smem > SMEM_CAP) return cudaErrorInvalidConfiguration;
+  const int grid = ceil_div(p.B, Bc) * RC;
+  switch (Bc) {
+    case 1: return launch_bwd_nr<1>(p, Bc, grid, smem, s);
+    case 2: return launch_bwd_nr<2>(p, Bc, grid, smem, s);
+    case 3: return launch_bwd_nr<3>(p, Bc, grid, smem, s);
+    default: return launch_bwd_nr<4>(p, Bc, grid, smem, s);
+  }
 }
 
 cudaError_t launch_rssm(const RssmParams &p, int nsm, cudaStream_t s, int *clusters_used) {

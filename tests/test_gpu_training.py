@@ -168,10 +168,12 @@ RSSM_BWD_SPECS = [
 @pytest.mark.parametrize("spec", RSSM_BWD_SPECS,
                          ids=lambda s: f"T{s.T}-B{s.B}-S{s.state_dim}-A{s.action_dim}-H{s.hidden}")
 @pytest.mark.parametrize("which", ["all", "beliefs_only"])
-def test_rssm_backward_parity(spec, which):
+@pytest.mark.parametrize("chain", ["fused", "launches"])
+def test_rssm_backward_parity(spec, which, chain):
     """rssm_backward + rssm_get_weight_grads against the oracle's RSSM backward
     (per tensor: max|gpu - ref| / max|ref| <= 1e-4); gradients given for every
-    output, or for the beliefs alone (the others NULL)."""
+    output, or for the beliefs alone (the others NULL); the reverse-time
+    chain as one cluster-resident kernel or as separate launches per step."""
     inp = wl.make_rssm_inputs(spec, seed=22)
     g = torch.Generator().manual_seed(97)
     T, B, S, RH = spec.T, spec.B, spec.state_dim, spec.rnn_hidden
@@ -182,6 +184,8 @@ def test_rssm_backward_parity(spec, which):
     dev = torch.device("cuda")
     m = binding.RSSM(spec.state_dim, spec.action_dim, spec.hidden, spec.rnn_hidden)
     m.set_weights(inp["weights"])
+    if chain == "launches":
+        binding.rssm_set_attr(m.h, binding.RCU_ATTR_FORCE_PATH, 1)
     with pytest.raises(RuntimeError, match="no rssm_backward"):
         binding.rssm_get_weight_grads(m.h, {})
     d = lambda t: None if t is None else t.to(dev)
@@ -190,6 +194,9 @@ def test_rssm_backward_parity(spec, which):
         **{k: d(v) for k, v in grads.items()})
     torch.cuda.synchronize()
     assert binding.rssm_get_status(m.h) == 0
+    # the fused chain is one launch for all T steps, the other ~9 per step
+    n_launch = binding.rssm_last_launch_count(m.h)
+    assert (n_launch < 60) if chain == "fused" else (n_launch > 5 * spec.T), n_launch
     ref = oracle.rssm_backward(inp["weights"], inp["actions"], inp["eps"], state0=inp["state0"],
                                belief0=inp["belief0"], **grads)
     pairs = [("dstate0", dstate0), ("dbelief0", dbelief0)]
