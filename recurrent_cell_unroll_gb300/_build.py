@@ -2,7 +2,10 @@
 
 Each .cu file is compiled to an object in parallel, then linked into
 ``recurrent_cell_unroll_gb300/_lib/librcu.so`` with the static CUDA runtime.
-Objects are rebuilt only when a source or header is newer.
+Objects are rebuilt only when a source or header is newer.  ``build(debug=True)``
+makes ``librcu_debug.so`` instead: the same sources with -DRCU_DEBUG, whose
+kernels check their global-memory indices and record a failed check in the
+device error word (RCU_ERR_CUDA from the status calls) instead of accessing.
 """
 from __future__ import annotations
 
@@ -19,6 +22,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "_lib")
 OBJDIR = os.path.join(LIBDIR, "obj")
 LIB = os.path.join(LIBDIR, "librcu.so")
+LIB_DEBUG = os.path.join(LIBDIR, "librcu_debug.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 
@@ -41,18 +45,20 @@ def _newest_header():
     return max((os.path.getmtime(h) for h in hs), default=0.0)
 
 
-def build(verbose: bool = False, jobs: int = 0) -> str:
-    os.makedirs(OBJDIR, exist_ok=True)
+def build(verbose: bool = False, jobs: int = 0, debug: bool = False) -> str:
+    objdir = OBJDIR + ("_debug" if debug else "")
+    lib = LIB_DEBUG if debug else LIB
+    os.makedirs(objdir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     hdr_t = _newest_header()
     cmds = []
     objs = []
     for s in srcs:
-        o = os.path.join(OBJDIR, os.path.basename(s)[:-3] + ".o")
+        o = os.path.join(objdir, os.path.basename(s)[:-3] + ".o")
         objs.append(o)
         if os.path.exists(o) and os.path.getmtime(o) >= max(os.path.getmtime(s), hdr_t):
             continue
-        cmds.append([nvcc(), *_flags(), "-c", s, "-o", o])
+        cmds.append([nvcc(), *_flags(), *(["-DRCU_DEBUG"] if debug else []), "-c", s, "-o", o])
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -65,12 +71,12 @@ def build(verbose: bool = False, jobs: int = 0) -> str:
     if cmds:
         with cf.ThreadPoolExecutor(max_workers=jobs or min(len(cmds), os.cpu_count() or 4)) as ex:
             list(ex.map(run, cmds))
-    if cmds or not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if cmds or not os.path.exists(lib) or os.path.getmtime(lib) < max(os.path.getmtime(o) for o in objs):
+        tmp = lib + f".tmp{os.getpid()}"
         run([nvcc(), ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static", "-lrt", "-ldl",
              "-lpthread"])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

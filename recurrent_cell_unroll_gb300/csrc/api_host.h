@@ -156,6 +156,7 @@ inline int status_from_dev(int v) {
     case rcu::DEV_TIMEOUT: return fail(RCU_ERR_TIMEOUT, "device step barrier timed out");
     case rcu::DEV_LENGTHS: return fail(RCU_ERR_LENGTHS, "a length was outside [1, T]");
     case rcu::DEV_CONFIG: return fail(RCU_ERR_CUDA, "a cluster kernel ran without its cluster shape");
+    case rcu::DEV_BOUNDS: return fail(RCU_ERR_CUDA, "a device bounds check (debug build) failed");
     default: return fail(RCU_ERR_CUDA, "unknown device status %d", v);
   }
 }

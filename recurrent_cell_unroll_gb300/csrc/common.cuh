@@ -11,7 +11,22 @@ namespace rcu {
 // DEV_CONFIG: a kernel that exchanges data between the CTAs of a thread-block
 // cluster found itself launched with another cluster shape, and returned
 // before touching any peer's shared memory.
-enum DevErr : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_LENGTHS = 2, DEV_CONFIG = 3 };
+// DEV_BOUNDS: a device bounds check of the RCU_DEBUG build failed (the
+// access was skipped).
+enum DevErr : int { DEV_OK = 0, DEV_TIMEOUT = 1, DEV_LENGTHS = 2, DEV_CONFIG = 3, DEV_BOUNDS = 4 };
+
+// Device bounds checks, compiled only into the debug build of the library
+// (-DRCU_DEBUG: recurrent_cell_unroll_gb300._build.build(debug=True)), the
+// stand-in for a memory checker.  RCU_DCHECK(cond, err) is true when `cond`
+// holds; otherwise it records DEV_BOUNDS in the error word `err` (first error
+// wins) and is false, so `if (RCU_DCHECK(...)) access;` skips the access.  In
+// the normal build it is the constant true and costs nothing.
+#ifdef RCU_DEBUG
+#define RCU_DCHECK(cond, err) \
+  ((cond) ? true : (atomicCAS((err), (int)::rcu::DEV_OK, (int)::rcu::DEV_BOUNDS), false))
+#else
+#define RCU_DCHECK(cond, err) true
+#endif
 
 enum Cell : int { CELL_LSTM = 0, CELL_GRU = 1 };
 

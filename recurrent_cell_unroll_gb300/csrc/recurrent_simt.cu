@@ -346,7 +346,8 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
       if (u < H) {
         const int tt = d == 0 ? step : lens[i] - 1 - step;
         const float *g = p.G + ((size_t)soff[tt] + i) * p.ldG + (size_t)d * nG * H + u;
-        for (int q = 0; q < nG; ++q) gpre[q] = __ldg(g + (size_t)q * H);
+        if (RCU_DCHECK(tt >= 0 && tt < p.T && (size_t)soff[tt] + i < (size_t)p.T * p.B, p.err))
+          for (int q = 0; q < nG; ++q) gpre[q] = __ldg(g + (size_t)q * H);
       }
     }
     have_pre = true;
@@ -422,7 +423,8 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
           gx[0] = gpre[0]; gx[1] = gpre[1]; gx[2] = gpre[2]; gx[3] = gpre[3];
         } else {
           const float *g = p.G + row * p.ldG + (size_t)d * nG * H + u;
-          for (int q = 0; q < nG; ++q) gx[q] = __ldg(g + (size_t)q * H);
+          if (RCU_DCHECK(tt >= 0 && tt < p.T && row < (size_t)p.T * B, p.err))
+            for (int q = 0; q < nG; ++q) gx[q] = __ldg(g + (size_t)q * H);
         }
         float hv;
         if (lstm) {
@@ -454,11 +456,13 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
         hnxt[(size_t)s * Kp + u] = Op<WT>::from_f(hv);
         const size_t yo = ((size_t)tt * B + sidx[s]) * ldo + (size_t)d * Hout + u;
         const size_t ymo = row * ldo + (size_t)d * Hout + u;
-        if (one) {  // written after the step's arrival
+        const bool out_ok = RCU_DCHECK(yo < (size_t)p.T * B * ldo && ymo < (size_t)p.T * B * ldo,
+                                       p.err);
+        if (one && out_ok) {  // written after the step's arrival
           yv = hv;
           y_at = yo;
           ym_at = ymo;
-        } else {
+        } else if (out_ok) {
           if (p.y) p.y[yo] = hv;
           if (p.ymid) reinterpret_cast<WT *>(p.ymid)[ymo] = Op<WT>::from_f(hv);
         }

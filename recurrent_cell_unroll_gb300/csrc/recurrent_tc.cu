@@ -369,6 +369,10 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
       if (!(row_ok && st < len)) return;
       const int tg = d == 0 ? st : len - 1 - st;
       const size_t grow = (size_t)p.meta.step_off[tg] + s;
+      if (!RCU_DCHECK(grow < (size_t)p.T * B &&
+                          (size_t)d * NG * H + (size_t)(NG - 1) * H + ub + nu <= (size_t)p.ldG,
+                      p.err))
+        return;
       const float *gp = p.G + grow * p.ldG + (size_t)d * NG * H + ub;
 #pragma unroll
       for (int g = 0; g < NG; ++g) {
@@ -468,7 +472,7 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
       }
       if (p.trace && threadIdx.x == 64) stamp(p, step, 13, globaltimer_ns());
       // exchange buffer for the next step (bf16 MMA operand): on the critical path
-      if (active) {
+      if (active && RCU_DCHECK(s < B && ub + nu <= Kp, p.err)) {
         __nv_bfloat16 *dst = hx + (size_t)(((step & 1) ^ 1) * B + s) * Kp + ub;
         if (nu == UPT) {
           __nv_bfloat162 lo = __floats2bfloat162_rn(h[0], h[1]);
@@ -498,7 +502,7 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
       // table, whose load the h_t store would otherwise wait behind)
       load_g(step + 1);
       // outputs leave the critical path: written after h_t is published
-      if (active && p.y) {
+      if (active && p.y && RCU_DCHECK(tt >= 0 && tt < p.T && b >= 0 && b < B, p.err)) {
         float *yo = p.y + ((size_t)tt * B + b) * ldo + (size_t)d * p.Hout + ub;
         if (vec_y) {
           *reinterpret_cast<float4 *>(yo) = make_float4(h[0], h[1], h[2], h[3]);
@@ -508,7 +512,8 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
             if (j < nu) yo[j] = h[j];
         }
       }
-      if (active && p.ymid) {
+      if (active && p.ymid &&
+          RCU_DCHECK((size_t)p.meta.step_off[tt] + s < (size_t)p.T * B, p.err)) {
         __nv_bfloat16 *ym = reinterpret_cast<__nv_bfloat16 *>(p.ymid) +
                             ((size_t)p.meta.step_off[tt] + s) * ldo + (size_t)d * p.Hout + ub;
 #pragma unroll

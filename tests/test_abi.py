@@ -151,3 +151,16 @@ def test_null_handle_errors_reach_rcu_last_error(lib):
         lib.rcu_last_error.restype = ctypes.c_char_p
         msg = lib.rcu_last_error().decode()
         assert name.split("_", 1)[0] in msg and "NULL handle" in msg, (name, msg)
+
+
+def test_debug_build_compiles_and_exports_the_same_symbols():
+    """The RCU_DEBUG build (device bounds checks recorded as an error code
+    instead of a faulting access) compiles and exports the same entry points."""
+    import subprocess
+    path = _build.build(debug=True)
+    assert path.endswith("librcu_debug.so") and os.path.exists(path)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True,
+                         text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert {n for n in exported if n.startswith(("rnn_", "rssm_", "rcu_"))} == \
+        set(declared_symbols())
