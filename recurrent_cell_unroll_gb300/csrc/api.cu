@@ -643,6 +643,7 @@ static int forward_layer_pipelined(rcu_rnn_t h, int T, int B, const void *X0, in
       TcRecParams tp;
       tp.base = pf;
       tp.ksplit = h->tc_ksplit;
+      tp.fixed_length = true;
       tp.Wtc[0] = tp.Wtc[1] = h->lw[l].fold_w.p;
       h->begin("recurrent_tc_lstmp", sl);
       cudaError_t e = launch_tc_recurrent(tp, h->nsm, sl);
@@ -841,6 +842,7 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
       TcRecParams tp;
       tp.base = pf;
       tp.ksplit = h->tc_ksplit;
+      tp.fixed_length = !varlen;
       for (int d = 0; d < D; ++d) tp.Wtc[d] = h->lw[(size_t)l * D + d].fold_w.p;
       h->begin("recurrent_tc_lstmp", s);
       cudaError_t e = launch_tc_recurrent(tp, h->nsm, s);
@@ -892,6 +894,7 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
       TcRecParams tp;
       tp.base = p;
       tp.ksplit = h->tc_ksplit;
+      tp.fixed_length = !varlen;
       for (int d = 0; d < D; ++d) tp.Wtc[d] = h->lw[(size_t)l * D + d].tc_whh.p;
       cudaError_t e = launch_tc_recurrent(tp, h->nsm, s);
       if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "tc recurrent: %s", cudaGetErrorString(e));

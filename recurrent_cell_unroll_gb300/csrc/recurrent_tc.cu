@@ -44,6 +44,14 @@ constexpr int MAX_STAGES = 8;
 struct Maps {
   CUtensorMap hx;    // [D*2*B rows][K cols], ld Kp, bf16, box 64 x a_rows
   CUtensorMap w[2];  // per direction [NU16*nG*16 rows][K cols], ld Kp, bf16, box 64 x N
+  // Tiled input and output streams (fixed-length batches: a step's rows are
+  // contiguous): G as [T][B][ldG] fp32 and the layer output as [T][B][ldo]
+  // (fp32 y, or bf16 packed rows for the next layer), boxes 16 columns x
+  // a_rows rows x 1 step.  Rows past B fall outside the box's step and are
+  // clipped (stores) or read as zero (loads).
+  CUtensorMap g, out;
+  int tiles;         // 1: G and the output move through these maps
+  int out_bf16;      // the output map is the bf16 one
   // h rows loaded per stage: 128, or round_up(B, 8) when one batch group
   // holds the whole batch (the stage's other rows are never read back: a
   // row of D depends only on the same row of A, and the epilogue skips rows
@@ -52,11 +60,12 @@ struct Maps {
 };
 
 struct Ctl {
-  uint64_t full[MAX_STAGES], empty[MAX_STAGES], wbar, tfull, tfree, mdone, xfull;
+  uint64_t full[MAX_STAGES], empty[MAX_STAGES], wbar, tfull, tfree, mdone, xfull, gbar;
   uint32_t tmem_base;
   int abort;
   int go;   // epilogue: result of the per-step accumulator wait, shared by all its threads
   int go2;  // epilogue: result of the per-step partial-sum wait (K split)
+  int g_issued;  // tiled G: loads issued into the G tile (thread 64's count)
   // K split: peer_sent[r] = steps whose partial sums CTA rank r of the
   // cluster sent to this CTA, stored here by rank r itself before the final
   // cluster barrier
@@ -70,10 +79,12 @@ struct Ctl {
 // memory).
 struct Geo {
   int N, nkb, nkbm, stages;
-  size_t w_bytes, x_bytes, smem;
+  size_t w_bytes, x_bytes, g_bytes, o_bytes, smem;
 };
 
-__host__ __device__ inline Geo make_geo(int nG, int K, int KS) {
+// tiles: reserve the G tile [nG][128 rows][16 units] fp32 and the output
+// tile [128 rows][16 units] (fp32 room) of the tiled streams
+__host__ __device__ inline Geo make_geo(int nG, int K, int KS, bool tiles = false) {
   Geo g;
   g.N = nG * UNITS * KS;
   g.nkb = ceil_div(K, BK);
@@ -81,7 +92,9 @@ __host__ __device__ inline Geo make_geo(int nG, int K, int KS) {
   g.w_bytes = (size_t)g.nkbm * g.N * 128;
   // partial sums received from the other KS-1 CTAs: [KS-1][nG][4][128] float4
   g.x_bytes = (size_t)(KS - 1) * nG * 4 * BG * 16;
-  const size_t fixed = 1024 + g.w_bytes + g.x_bytes + 256;
+  g.g_bytes = tiles ? (size_t)nG * BG * UNITS * 4 : 0;
+  g.o_bytes = tiles ? (size_t)BG * UNITS * 4 : 0;
+  const size_t fixed = 1024 + g.w_bytes + g.x_bytes + g.g_bytes + g.o_bytes + 256;
   int st = (int)((SMEM_LIMIT - (long long)fixed) / A_STAGE);
   g.stages = st > MAX_STAGES ? MAX_STAGES : st;
   g.smem = fixed + (size_t)(g.stages > 0 ? g.stages : 0) * A_STAGE;
@@ -90,6 +103,33 @@ __host__ __device__ inline Geo make_geo(int nG, int K, int KS) {
 
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// 3D TMA load / store of a box at (x, y, z); the store is committed as a
+// bulk group, its shared-memory reads waited for with bulk_wait_read
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(tc::smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(tc::smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *smem_src, int x,
+                                             int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];\n\t"
+      "cp.async.bulk.commit_group;" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(tc::smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 // Step trace: CTA 0's stamps for every step, and (RCU_ATTR_TRACE = 2) every
 // CTA's stamps for a window of steps.  Called by one thread per stamp.
@@ -136,12 +176,14 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
-  const Geo geo = make_geo(NG, p.Hout, KS);
+  const Geo geo = make_geo(NG, p.Hout, KS, maps.tiles != 0);
   const int N = geo.N, STG = geo.stages;
   uint8_t *sW = smem;                       // resident B operand, nkbm blocks of N x 128 B
   uint8_t *sA = smem + geo.w_bytes;         // ring of STG stages of 128 x 128 B
   float4 *xbuf = reinterpret_cast<float4 *>(sA + (size_t)STG * A_STAGE);
-  Ctl *ctl = reinterpret_cast<Ctl *>(reinterpret_cast<uint8_t *>(xbuf) + geo.x_bytes);
+  float *gtile = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(xbuf) + geo.x_bytes);
+  uint8_t *otile = reinterpret_cast<uint8_t *>(gtile) + geo.g_bytes;
+  Ctl *ctl = reinterpret_cast<Ctl *>(otile + geo.o_bytes);
 
   const int NU = p.NU, NBG = ceil_div(p.B, BG);  // NU = CTAs per (direction, batch group)
   const int d = blockIdx.x / (NBG * NU);
@@ -180,6 +222,8 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
     // partial sums from the peer: this CTA's own arrival with the expected
     // byte count, completed by the peer's asynchronous stores
     tc::mbar_init(&ctl->xfull, 1);
+    tc::mbar_init(&ctl->gbar, 1);
+    ctl->g_issued = 0;
     ctl->abort = 0;
     for (int i = 0; i < 4; ++i) ctl->peer_sent[i] = 0;
     tc::fence_mbar_init();
@@ -385,15 +429,50 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
         }
       }
     };
-    load_g(0);
+    // tiled G: thread 64 loads step st's [nG][rows][16 units] tile (every row
+    // of a fixed-length batch runs every step, so the step's rows are
+    // contiguous), counted on gbar
+    const bool tiles = maps.tiles != 0;
+    int g_done = 0;  // thread 64: G tiles waited for
+    auto issue_g = [&](int st) {
+      const int tg = d == 0 ? st : Tg - 1 - st;
+      tc::mbar_arrive_expect_tx(&ctl->gbar, (uint32_t)(NG * UNITS * 4 * maps.a_rows));
+#pragma unroll
+      for (int g = 0; g < NG; ++g)
+        tma_load_3d(gtile + (size_t)g * BG * UNITS, &maps.g, &ctl->gbar, d * NG * H + g * H + u0,
+                    row0, tg);
+      ++ctl->g_issued;
+    };
+    if (tiles) {
+      if (threadIdx.x == 64 && Tg > 0) issue_g(0);
+    } else {
+      load_g(0);
+    }
     for (int step = 0; step < Tg; ++step) {
       const bool active = row_ok && step < len;
       const int tt = d == 0 ? step : len - 1 - step;
-      // one thread waits for the accumulator; its result is shared so that
-      // all epilogue threads leave the loop together
-      if (threadIdx.x == 64) ctl->go = tc::mbar_wait(&ctl->tfull, step & 1, p.err, abort, tmo);
+      // one thread waits for the accumulator (and the step's G tile); its
+      // result is shared so that all epilogue threads leave the loop together
+      if (threadIdx.x == 64) {
+        // the output tile is rewritten below: its previous store has read it
+        if (tiles) bulk_wait_read();
+        bool ok = tc::mbar_wait(&ctl->tfull, step & 1, p.err, abort, tmo);
+        if (ok && tiles) {
+          ok = tc::mbar_wait(&ctl->gbar, (uint32_t)step & 1u, p.err, abort, tmo);
+          if (ok) ++g_done;
+        }
+        ctl->go = ok;
+      }
       epi_bar();
       if (!ctl->go) break;
+      if (tiles) {
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          const float4 f =
+              *reinterpret_cast<const float4 *>(gtile + ((size_t)g * BG + r) * UNITS + part * UPT);
+          gx[g][0] = f.x; gx[g][1] = f.y; gx[g][2] = f.z; gx[g][3] = f.w;
+        }
+      }
       tc::tc_fence_after();
       if (p.trace && threadIdx.x == 64) stamp(p, step, 3, globaltimer_ns());
       float acc[NG][UPT];
@@ -487,6 +566,21 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
             if (j < nu) dst[j] = __float2bfloat16_rn(h[j]);
         }
       }
+      if (tiles && row_ok) {
+        // the layer output of this row and units, for one TMA store per step
+        if (maps.out_bf16) {
+          __nv_bfloat162 lo = __floats2bfloat162_rn(h[0], h[1]);
+          __nv_bfloat162 hi = __floats2bfloat162_rn(h[2], h[3]);
+          uint2 pk;
+          pk.x = *reinterpret_cast<uint32_t *>(&lo);
+          pk.y = *reinterpret_cast<uint32_t *>(&hi);
+          *reinterpret_cast<uint2 *>(otile + ((size_t)r * UNITS + part * UPT) * 2) = pk;
+        } else {
+          *reinterpret_cast<float4 *>(otile + ((size_t)r * UNITS + part * UPT) * 4) =
+              make_float4(h[0], h[1], h[2], h[3]);
+        }
+        fence_proxy_async_shared();
+      }
       if (p.trace && threadIdx.x == 64) stamp(p, step, 6, globaltimer_ns());
       fence_proxy_async_global();
       epi_bar();
@@ -496,13 +590,20 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
         // barrier above) before the arrival
         red_release_gpu_add(ctr, 1u);
         if (p.trace) stamp(p, step, 4, globaltimer_ns());
+        if (tiles) {
+          // off the critical path: the step's output tile, and the next
+          // step's G tile (every thread read this step's above)
+          if (u0 < p.Hout)
+            tma_store_3d(&maps.out, otile, d * p.Hout + u0, row0, d == 0 ? step : Tg - 1 - step);
+          if (step + 1 < Tg) issue_g(step + 1);
+        }
       }
       // the next step's G: loaded after the release (a release waits for the
       // thread's earlier loads too, and the address needs the step offset
       // table, whose load the h_t store would otherwise wait behind)
-      load_g(step + 1);
+      if (!tiles) load_g(step + 1);
       // outputs leave the critical path: written after h_t is published
-      if (active && p.y && RCU_DCHECK(tt >= 0 && tt < p.T && b >= 0 && b < B, p.err)) {
+      if (!tiles && active && p.y && RCU_DCHECK(tt >= 0 && tt < p.T && b >= 0 && b < B, p.err)) {
         float *yo = p.y + ((size_t)tt * B + b) * ldo + (size_t)d * p.Hout + ub;
         if (vec_y) {
           *reinterpret_cast<float4 *>(yo) = make_float4(h[0], h[1], h[2], h[3]);
@@ -512,7 +613,7 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
             if (j < nu) yo[j] = h[j];
         }
       }
-      if (active && p.ymid &&
+      if (!tiles && active && p.ymid &&
           RCU_DCHECK((size_t)p.meta.step_off[tt] + s < (size_t)p.T * B, p.err)) {
         __nv_bfloat16 *ym = reinterpret_cast<__nv_bfloat16 *>(p.ymid) +
                             ((size_t)p.meta.step_off[tt] + s) * ldo + (size_t)d * p.Hout + ub;
@@ -530,6 +631,16 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
       }
     }
     if (KS > 1) x_left = x_done < x_posted ? -x_done - 1 : x_done;  // < 0: phase x_done armed
+    if (tiles && threadIdx.x == 64) {
+      // output stores complete, and a G tile still landing lands, before the
+      // CTA's shared memory goes away (at most one is outstanding)
+      bulk_wait_all();
+      if (ctl->g_issued > g_done) {
+        volatile int never = 0;
+        tc::mbar_wait(&ctl->gbar, (uint32_t)(ctl->g_issued - 1) & 1u, nullptr, &never,
+                      100000000ull);
+      }
+    }
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -606,6 +717,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
   });
   return fn;
+}
+
+// [T][rows][cols] (row stride ld elements of esz bytes), box 16 columns x
+// box_rows rows x 1, no swizzle: the tiled G and output streams
+bool make_map_steps(CUtensorMap *map, const void *base, bool bf16, int T, int rows, int cols,
+                    int ld, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const size_t esz = bf16 ? 2 : 4;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * esz, (cuuint64_t)ld * esz * rows};
+  cuuint32_t box[3] = {(cuuint32_t)UNITS, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+            const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool make_map(CUtensorMap *map, const void *base, long long rows, int cols, int ld, int box_rows) {
@@ -728,8 +856,27 @@ cudaError_t launch_tc_recurrent(const TcRecParams &tp, int nsm, cudaStream_t s) 
   if (ks == 0) ks = 2;
   while (ks > 1 && !ks_fits(nG, p.Hout, ks)) ks /= 2;
 
+  // Tiled G and output streams: fixed-length batches (a step's rows are
+  // contiguous), one output (y, or the bf16 rows of the next layer), 16-byte
+  // aligned rows and bases, whole 16-unit tiles of the output, and a ring of
+  // at least 4 h stages beside the tiles
+  const bool y_out = p.y != nullptr, m_out = p.ymid != nullptr;
+  const int ldo = p.D * p.Hout;
+  auto aligned16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
+  const bool tiles_ok = tp.fixed_length && (y_out != m_out) && (p.H % 4) == 0 &&
+                        (p.Hout % UNITS) == 0 && ((size_t)p.ldG * 4) % 16 == 0 &&
+                        ((size_t)ldo * (y_out ? 4 : 2)) % 16 == 0 && aligned16(p.G) &&
+                        aligned16(y_out ? (const void *)p.y : p.ymid);
+
   for (int attempt = 0; attempt < 3; ++attempt) {
-    const Geo geo = make_geo(nG, p.Hout, ks);
+    maps.tiles = tiles_ok && make_geo(nG, p.Hout, ks, true).stages >= 4 ? 1 : 0;
+    const Geo geo = make_geo(nG, p.Hout, ks, maps.tiles != 0);
+    maps.out_bf16 = m_out ? 1 : 0;
+    if (maps.tiles &&
+        (!make_map_steps(&maps.g, p.G, false, p.T, p.B, p.ldG, p.ldG, maps.a_rows) ||
+         !make_map_steps(&maps.out, y_out ? (const void *)p.y : p.ymid, m_out, p.T, p.B, ldo, ldo,
+                         maps.a_rows)))
+      return cudaErrorInvalidValue;
     p.NU = ks > 1 ? ks * ceil_div(p.H, ks * UNITS) : NU16;
     for (int d = 0; d < 2; ++d) {
       const void *w = tp.Wtc[d < p.D ? d : 0];

@@ -24,6 +24,7 @@ struct TcRecParams {
   RecParams base;
   const void *Wtc[2];  // tensor-core packed W_hh per direction (tc_pack_whh)
   int ksplit = 0;      // CTAs splitting K: 0 = automatic (2), 1 = none, 2 or 4 = a cluster
+  bool fixed_length = false;  // no lengths: every row runs every step (tiled G and outputs)
 };
 // weights can be packed for the tensor-core kernel (shape only)
 bool tc_rec_packable(int cell, int H, int Hout, int P);
