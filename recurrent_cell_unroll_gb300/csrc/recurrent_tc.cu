@@ -413,6 +413,7 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
       if (!(row_ok && st < len)) return;
       const int tg = d == 0 ? st : len - 1 - st;
       const size_t grow = (size_t)p.meta.step_off[tg] + s;
+      if (nu == 0) return;  // no unit of this thread exists
       if (!RCU_DCHECK(grow < (size_t)p.T * B &&
                           (size_t)d * NG * H + (size_t)(NG - 1) * H + ub + nu <= (size_t)p.ldG,
                       p.err))
