@@ -552,7 +552,7 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
       }
       if (p.trace && threadIdx.x == 64) stamp(p, step, 13, globaltimer_ns());
       // exchange buffer for the next step (bf16 MMA operand): on the critical path
-      if (active && RCU_DCHECK(s < B && ub + nu <= Kp, p.err)) {
+      if (active && nu > 0 && RCU_DCHECK(s < B && ub + nu <= Kp, p.err)) {
         __nv_bfloat16 *dst = hx + (size_t)(((step & 1) ^ 1) * B + s) * Kp + ub;
         if (nu == UPT) {
           __nv_bfloat162 lo = __floats2bfloat162_rn(h[0], h[1]);
