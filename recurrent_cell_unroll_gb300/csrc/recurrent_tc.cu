@@ -46,9 +46,11 @@ struct Maps {
   CUtensorMap w[2];  // per direction [NU16*nG*16 rows][K cols], ld Kp, bf16, box 64 x N
   // Tiled input and output streams (fixed-length batches: a step's rows are
   // contiguous): G as [T][B][ldG] fp32 and the layer output as [T][B][ldo]
-  // (fp32 y, or bf16 packed rows for the next layer), boxes 16 columns x
-  // a_rows rows x 1 step.  Rows past B fall outside the box's step and are
-  // clipped (stores) or read as zero (loads).
+  // (fp32 y, or bf16 packed rows for the next layer), boxes of 16 bytes of
+  // columns (4 fp32 or 8 bf16) x a_rows rows x 1 step, so that in shared
+  // memory each box is a strip of 16-byte rows: a warp's 32 rows of one
+  // strip are 512 contiguous bytes (no bank conflicts).  Rows past B fall
+  // outside the box's step and are clipped (stores) or read as zero (loads).
   CUtensorMap g, out;
   int tiles;         // 1: G and the output move through these maps
   int out_bf16;      // the output map is the bf16 one
@@ -440,8 +442,10 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
       tc::mbar_arrive_expect_tx(&ctl->gbar, (uint32_t)(NG * UNITS * 4 * maps.a_rows));
 #pragma unroll
       for (int g = 0; g < NG; ++g)
-        tma_load_3d(gtile + (size_t)g * BG * UNITS, &maps.g, &ctl->gbar, d * NG * H + g * H + u0,
-                    row0, tg);
+#pragma unroll
+        for (int q4 = 0; q4 < UNITS / UPT; ++q4)  // strip [g][q4]: 4 units x rows
+          tma_load_3d(gtile + ((size_t)g * (UNITS / UPT) + q4) * BG * UPT, &maps.g, &ctl->gbar,
+                      d * NG * H + g * H + u0 + q4 * UPT, row0, tg);
       ++ctl->g_issued;
     };
     if (tiles) {
@@ -470,7 +474,7 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
           const float4 f =
-              *reinterpret_cast<const float4 *>(gtile + ((size_t)g * BG + r) * UNITS + part * UPT);
+              *reinterpret_cast<const float4 *>(gtile + (((size_t)g * (UNITS / UPT) + part) * BG + r) * UPT);
           gx[g][0] = f.x; gx[g][1] = f.y; gx[g][2] = f.z; gx[g][3] = f.w;
         }
       }
@@ -575,9 +579,10 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
           uint2 pk;
           pk.x = *reinterpret_cast<uint32_t *>(&lo);
           pk.y = *reinterpret_cast<uint32_t *>(&hi);
-          *reinterpret_cast<uint2 *>(otile + ((size_t)r * UNITS + part * UPT) * 2) = pk;
+          // bf16 strips of 8 units (16-byte rows): part pairs share one
+          *reinterpret_cast<uint2 *>(otile + (((size_t)(part >> 1) * BG + r) * 2 * UPT + (part & 1) * UPT) * 2) = pk;
         } else {
-          *reinterpret_cast<float4 *>(otile + ((size_t)r * UNITS + part * UPT) * 4) =
+          *reinterpret_cast<float4 *>(otile + ((size_t)part * BG + r) * UPT * 4) =
               make_float4(h[0], h[1], h[2], h[3]);
         }
         fence_proxy_async_shared();
@@ -594,8 +599,13 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
         if (tiles) {
           // off the critical path: the step's output tile, and the next
           // step's G tile (every thread read this step's above)
-          if (u0 < p.Hout)
-            tma_store_3d(&maps.out, otile, d * p.Hout + u0, row0, d == 0 ? step : Tg - 1 - step);
+          if (u0 < p.Hout) {
+            // one store per strip: 4 fp32 or 8 bf16 units of every row
+            const int su = maps.out_bf16 ? 2 * UPT : UPT, ns = UNITS / su;
+            for (int q4 = 0; q4 < ns; ++q4)
+              tma_store_3d(&maps.out, otile + (size_t)q4 * BG * su * (maps.out_bf16 ? 2 : 4),
+                           d * p.Hout + u0 + q4 * su, row0, d == 0 ? step : Tg - 1 - step);
+          }
           if (step + 1 < Tg) issue_g(step + 1);
         }
       }
@@ -720,8 +730,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// [T][rows][cols] (row stride ld elements of esz bytes), box 16 columns x
-// box_rows rows x 1, no swizzle: the tiled G and output streams
+// [T][rows][cols] (row stride ld elements of esz bytes), box 16 bytes of
+// columns x box_rows rows x 1, no swizzle: the tiled G and output streams
 bool make_map_steps(CUtensorMap *map, const void *base, bool bf16, int T, int rows, int cols,
                     int ld, int box_rows) {
   auto fn = encode_fn();
@@ -729,7 +739,7 @@ bool make_map_steps(CUtensorMap *map, const void *base, bool bf16, int T, int ro
   const size_t esz = bf16 ? 2 : 4;
   cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)T};
   cuuint64_t strides[2] = {(cuuint64_t)ld * esz, (cuuint64_t)ld * esz * rows};
-  cuuint32_t box[3] = {(cuuint32_t)UNITS, (cuuint32_t)box_rows, 1};
+  cuuint32_t box[3] = {(cuuint32_t)(16 / esz), (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
             const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
