@@ -677,10 +677,22 @@ def run_e2e(args, spec, e2e_io, status, keep, dev, stream, local, device_ms):
         h2d = sum(v.numel() * v.element_size() for v in host_in)
         d2h = sum(o.numel() * o.element_size() for o in host_out)
         e2e_steps = max(1, args.e2e_steps)
-        # untimed warm-up calls: the first calls after the staging buffers and
-        # copy streams are set up run slower (one measured 3x the steady step)
-        for _ in range(max(3, args.warmup)):
+        # untimed warm-up calls until the call time is steady: the first calls
+        # after the staging buffers, copy streams and pinned buffers are set
+        # up ran up to 3x slower than the steady step (two in a row within
+        # 10 %, at least W calls, at most 20)
+        prev, warm = None, 0
+        while warm < 20:
+            wa, wb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            wa.record(stream)
             host_call()
+            wb.record(stream)
+            torch.cuda.synchronize(dev)
+            cur = wa.elapsed_time(wb)
+            warm += 1
+            if warm >= max(3, args.warmup) and prev is not None and abs(cur - prev) <= 0.1 * prev:
+                break
+            prev = cur
         dist_barrier()
         torch.cuda.synchronize(dev)
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -705,6 +717,7 @@ def run_e2e(args, spec, e2e_io, status, keep, dev, stream, local, device_ms):
     return {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
             "ms_per_step_each": [round(x, 3) for x in per], "steps": e2e_steps,
+            "warmup_calls": warm,
             "device_ms_per_step": round(device_ms, 4),
             "link": link,
             "h2d_ms_alone": round(h2d / (link["h2d_gbs"] * 1e9) * 1e3, 3),
