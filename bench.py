@@ -440,7 +440,6 @@ def make_train_runner(spec, inp, dev, net, d):
 # workloads (the mean over the captured launches); a kernel changed after its
 # capture must be taken out of this table (its traffic is then null).
 TRAFFIC = {
-    ("gru_bf16_3L_T512_B256_1024", "recurrent_tc"): 1960.8e6,
     ("lstmp_bf16_2L_T1000_B32_80x1024p256", "recurrent_tc_lstmp"): 43.7e6,
     ("bilstm_f32_varlen_B64_T500_256x512", "recurrent_simt"): 357.9e6,
     ("lstm_f32_T80_B1_512x256", "recurrent_cluster"): 1.41e6,
@@ -480,6 +479,14 @@ def roofline(spec, inp, prof, peaks, nsm, step_ms=None, region_s=None, steps=1):
     return r
 
 
+def on_tensor_cores(kernel):
+    """The kernels named *_tc* (the bf16 input GEMM and the tcgen05
+    recurrences) run their contraction on the tensor cores; every other kernel
+    (the SIMT and cluster-resident recurrences, the whole backward pass) is
+    FP32 FFMA work, even on a bf16 handle."""
+    return "_tc" in kernel
+
+
 def _roofline(spec, inp, prof, peaks, nsm, step_ms=None, region_s=None, steps=1):
     if isinstance(spec, wl.RssmSpec) and not spec.train:
         # one kernel per step: its launch time is the event-timed step
@@ -504,7 +511,7 @@ def _roofline(spec, inp, prof, peaks, nsm, step_ms=None, region_s=None, steps=1)
     per_launch = sum(fl[kind]) * steps / n
     avg_s = ms / 1e3 / n
     achieved = per_launch / avg_s / 1e12
-    if getattr(spec, "dtype", "f32") == "bf16":
+    if on_tensor_cores(name):
         peak, note = bf16_peak(peaks, region_s)
         bound = "tensor"
     else:

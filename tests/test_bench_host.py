@@ -170,7 +170,7 @@ def test_traffic_table_names_real_workloads_and_kernels():
     name the roofline can report for it."""
     names = {s.name for s in bench.WORKLOADS.values()}
     kinds = {"recurrent_tc", "recurrent_tc_lstmp", "recurrent_simt", "recurrent_cluster",
-             "rssm_unroll", "bwd_recurrent"}
+             "rssm_unroll", "bwd_recurrent", "rssm_bwd_chain"}
     for (workload, kernel), traffic in bench.TRAFFIC.items():
         assert workload in names, workload
         assert kernel in kinds, kernel
