@@ -493,17 +493,35 @@ static int ensure_ws(rcu_rnn_s *h, int T, int B) {
 static int lp_chunks(int T) { return std::min(32, std::max(2, T / 64)); }
 
 static bool layer_pipeline_ok(rcu_rnn_t h, int T, int B, bool varlen, bool bf) {
-  if (!h->layer_pipeline || !bf || h->P == 0 || h->D != 1 || h->layers < 2 || varlen ||
-      h->pclip || h->force_path == 1 || h->trace || !h->mbuf || T < 128)
+  if (!h->layer_pipeline || !bf || h->D != 1 || h->layers < 2 || varlen || h->pclip ||
+      h->force_path == 1 || h->trace || T < 128)
     return false;
   const int H = h->H, P = h->P;
-  if ((H % 8) != 0 || !tc_rec_supported(RCU_LSTM, H, H, 0, h->nsm, B, 1) ||
-      !tc_gemm_supported(H, P))
+  if ((H % 8) != 0) return false;
+  if (P > 0) {
+    if (!h->mbuf || !tc_rec_supported(RCU_LSTM, H, H, 0, h->nsm, B, 1) || !tc_gemm_supported(H, P))
+      return false;
+    for (int l = 0; l < h->layers; ++l)
+      if (!h->lw[l].fold_w.p || !tc_gemm_supported(h->in_l[l], h->nG * H)) return false;
+    // two recurrences side by side, and room beside one of them for the GEMMs
+    const int rg = tc_rec_grid(RCU_LSTM, H, H, B, 1, h->tc_ksplit);
+    return 2 * rg <= h->nsm && h->nsm - rg >= 16;
+  }
+  // No projection: only where the layer-by-layer forward would take the
+  // tensor-core recurrence, and without the training pass's kept outputs.
+  if (h->force_path == 3 || h->keep_out || !tc_rec_supported(h->cell, H, H, 0, h->nsm, B, 1))
+    return false;
+  ClusterRecPlan cp{};
+  if (h->force_path == 0 && h->lw[0].cl_whh.p &&
+      plan_recurrent_cluster(&cp, h->cell, H, H, T, B, 1, bf, 16))
     return false;
   for (int l = 0; l < h->layers; ++l)
-    if (!h->lw[l].fold_w.p || !tc_gemm_supported(h->in_l[l], h->nG * H)) return false;
-  // two recurrences side by side, and room beside one of them for the GEMMs
-  const int rg = tc_rec_grid(RCU_LSTM, H, H, B, 1, h->tc_ksplit);
+    if (!h->lw[l].tc_whh.p || !tc_gemm_supported(h->in_l[l], h->nG * H)) return false;
+  // Only where two layers' recurrences fit side by side (as for LSTMP): a
+  // recurrence that fills the GPU (the 3-layer GRU's 128 CTAs) gains ~1 %
+  // from chunking, since the next layer's GEMM then runs on the few SMs left
+  // and its memory traffic slows the latency-bound steps beside it.
+  const int rg = tc_rec_grid(h->cell, H, H, B, 1, h->tc_ksplit);
   return 2 * rg <= h->nsm && h->nsm - rg >= 16;
 }
 
@@ -511,10 +529,15 @@ static int forward_layer_pipelined(rcu_rnn_t h, int T, int B, const void *X0, in
                                    const float *h0, const float *c0, float *y, float *h_n,
                                    float *c_n, int *err, cudaStream_t s) {
   const int L = h->layers, H = h->H, P = h->P, nG = h->nG, G4 = nG * H;
+  // proj: LSTMP, whose recurrence runs on m with W_hh W_hr folded, each
+  // chunk's projection a GEMM; otherwise the layer's own recurrence writes
+  // the next layer's bf16 input (or y) directly
+  const bool proj = P > 0;
+  const int rcell = proj ? RCU_LSTM : h->cell, Ho = proj ? P : H;
   const int ldH = round_up(H, 8);
   const int n = lp_chunks(T);
   const int Tc = ceil_div(T, n), nch = ceil_div(T, Tc), Tl = T - (nch - 1) * Tc;
-  const int rg = tc_rec_grid(RCU_LSTM, H, H, B, 1, h->tc_ksplit);
+  const int rg = tc_rec_grid(rcell, H, H, B, 1, h->tc_ksplit);
   const int gemm_sms = std::max(16, h->nsm - rg);
   const int cstride = std::max(4, tc_rec_counters(B, 1));
   // resources
@@ -578,9 +601,11 @@ static int forward_layer_pipelined(rcu_rnn_t h, int T, int B, const void *X0, in
       cudaStream_t sl = stream_of(l);
       const bool last = l == L - 1;
       if (l > 0) {
-        // layer l-1 finished chunk c: project it, convert, and form this
-        // layer's gate pre-activations for the chunk
+        // layer l-1 finished chunk c: project it and convert (LSTMP), and
+        // form this layer's gate pre-activations for the chunk
         CU(cudaStreamWaitEvent(sl, ev[(l - 1) * nch + c], 0));
+      }
+      if (l > 0 && proj) {
         float *Yp = h->keep_out ? h->keep_out + (size_t)(l - 1) * T * B * P : h->ytmp;
         h->begin("projection_gemm_tc", sl);
         cudaError_t e = launch_tc_gemm(mbuf + r0 * H, H, (const __nv_bfloat16 *)h->lw[l - 1].whr_bf.p,
@@ -597,16 +622,21 @@ static int forward_layer_pipelined(rcu_rnn_t h, int T, int B, const void *X0, in
         CU(launch_convert<__nv_bfloat16>(Yp + r0 * P, (__nv_bfloat16 *)h->ymid + r0 * P,
                                          (size_t)tc * B * P, sl));
         h->end(sl);
+      }
+      if (l > 0) {
+        // (rows [r0, r0 + tc*B) of ymid hold layer l-1's output for the chunk;
+        // this layer's recurrence overwrites them only after this GEMM)
         h->begin("input_gemm_tc", sl);
-        e = launch_tc_gemm((const __nv_bfloat16 *)h->ymid + r0 * P, P,
-                           (const __nv_bfloat16 *)h->wih[l].p, round_up(h->in_l[l], 8),
-                           (const float *)h->gbias[l].p, G + r0 * G4, G4, tc * B, nullptr, G4,
-                           h->in_l[l], gemm_sms, sl, err, (uint64_t)h->timeout_ns);
+        cudaError_t e = launch_tc_gemm((const __nv_bfloat16 *)h->ymid + r0 * Ho, Ho,
+                                       (const __nv_bfloat16 *)h->wih[l].p, round_up(h->in_l[l], 8),
+                                       (const float *)h->gbias[l].p, G + r0 * G4, G4, tc * B,
+                                       nullptr, G4, h->in_l[l], gemm_sms, sl, err,
+                                       (uint64_t)h->timeout_ns);
         h->end(sl);
         if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "tc gemm: %s", cudaGetErrorString(e));
       }
       // the layer's initial projected state enters as W_hh h0 in the first step's G
-      if (c == 0 && h0) {
+      if (proj && c == 0 && h0) {
         h->begin("h0_gates", sl);
         CU(launch_h0_gates(G, G4, (const float *)h->lw[l].whh_f32.p, h0 + (size_t)l * B * P, B,
                            tc, G4, P, 0, sl));
@@ -618,21 +648,30 @@ static int forward_layer_pipelined(rcu_rnn_t h, int T, int B, const void *X0, in
       float *c_out = st + (size_t)(2 + (c & 1)) * B * H;
       RecParams pf{};
       pf.T = tc; pf.B = B; pf.H = H; pf.Hout = H; pf.Kp = ldH; pf.Hp = h->Hp; pf.nG = nG; pf.D = 1;
-      pf.cell = RCU_LSTM; pf.proj = 0;
+      pf.cell = rcell; pf.proj = 0;
       pf.U = h->U; pf.NU = h->NU; pf.Rp = h->Rp;
       pf.meta = mc[c + 1 < nch ? 0 : 1];
       pf.G = G + r0 * G4;
       pf.ldG = G4;
-      pf.bhn[0] = pf.bhn[1] = nullptr;
-      // m_{-1} does not enter the first chunk (W_hh h0 is in G); later chunks
-      // start from the previous chunk's m, rounded to bf16 by the kernel as
-      // every step's exchange is
-      pf.h0 = c == 0 ? nullptr : m_in;
-      pf.c0 = c == 0 ? (c0 ? c0 + (size_t)l * B * H : nullptr) : c_in;
-      pf.h_n = m_out;
-      pf.c_n = (c == nch - 1 && c_n) ? c_n + (size_t)l * B * H : c_out;
-      pf.y = nullptr;
-      pf.ymid = mbuf + r0 * H;
+      pf.bhn[0] = proj ? nullptr : (const float *)h->lw[l].bhn.p;
+      pf.bhn[1] = nullptr;
+      // LSTMP: m_{-1} does not enter the first chunk (W_hh h0 is in G).  Later
+      // chunks start from the previous chunk's state (m or h, and c), rounded
+      // to bf16 by the kernel as every step's exchange is.
+      const float *h0l = (!proj && h0) ? h0 + (size_t)l * B * H : nullptr;
+      pf.h0 = c == 0 ? h0l : m_in;
+      if (nG == 4) {
+        pf.c0 = c == 0 ? (c0 ? c0 + (size_t)l * B * H : nullptr) : c_in;
+        pf.c_n = (c == nch - 1 && c_n) ? c_n + (size_t)l * B * H : c_out;
+      }
+      pf.h_n = (!proj && c == nch - 1 && h_n) ? h_n + (size_t)l * B * H : m_out;
+      if (proj) {
+        pf.y = nullptr;
+        pf.ymid = mbuf + r0 * H;
+      } else {
+        pf.y = last ? y + r0 * H : nullptr;
+        pf.ymid = last ? nullptr : (__nv_bfloat16 *)h->ymid + r0 * H;
+      }
       pf.hx = (char *)h->lp_hx.p + (size_t)l * 2 * B * ldH * 2;
       pf.mx = h->mx; pf.hst = h->hst; pf.cst = h->cst;
       pf.ctr = (unsigned *)h->lp_ctl.p + ((size_t)l * nch + c) * cstride;
@@ -644,13 +683,13 @@ static int forward_layer_pipelined(rcu_rnn_t h, int T, int B, const void *X0, in
       tp.base = pf;
       tp.ksplit = h->tc_ksplit;
       tp.fixed_length = true;
-      tp.Wtc[0] = tp.Wtc[1] = h->lw[l].fold_w.p;
-      h->begin("recurrent_tc_lstmp", sl);
+      tp.Wtc[0] = tp.Wtc[1] = proj ? h->lw[l].fold_w.p : h->lw[l].tc_whh.p;
+      h->begin(proj ? "recurrent_tc_lstmp" : "recurrent_tc", sl);
       cudaError_t e = launch_tc_recurrent(tp, h->nsm, sl);
       h->end(sl);
       if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "tc recurrent: %s", cudaGetErrorString(e));
       CU(cudaEventRecord(ev[l * nch + c], sl));
-      if (last) {
+      if (last && proj) {
         // the last layer's projection of the chunk, straight into y
         h->begin("projection_gemm_tc", sl);
         e = launch_tc_gemm(mbuf + r0 * H, H, (const __nv_bfloat16 *)h->lw[l].whr_bf.p, ldH,
