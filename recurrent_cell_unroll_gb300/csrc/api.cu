@@ -97,7 +97,7 @@ struct rcu_rnn_s : EventProfiler {
   cudaStream_t cp_in = nullptr, cp_out = nullptr;
   std::vector<cudaEvent_t> chunk_ev;
   DevBuf io_xc[2], io_yc[2], io_st[2], io_ct[2];
-  // layer-pipelined LSTMP forward: one stream per layer past the first,
+  // layer-pipelined forward: one stream per layer past the first,
   // events between them, per-(layer, chunk) step counters, per-layer
   // exchange buffers and chunk-boundary states, chunk metadata
   std::vector<cudaStream_t> lp_streams;
@@ -107,6 +107,7 @@ struct rcu_rnn_s : EventProfiler {
   // rnn_backward: workspace, per-layer weight gradients of the last call, and
   // the forward's per-layer outputs (layer l < L-1 written to keep_out + l*T*B*Hout)
   DevBuf bw;
+  DevBuf bwb;  // bf16 handles: the bf16 operands of the backward's tensor-core GEMMs
   std::vector<DevBuf> gw;
   bool grads_ready = false;
   float *keep_out = nullptr;
@@ -1196,6 +1197,27 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
         *TMP = wsf + o_tmp, *DYM = wsf + o_dym, *XM = wsf + o_xm;
   float *CR = (cell == RCU_LSTM && h->cclip) ? wsf + o_cr : nullptr;
   unsigned *ctr = (unsigned *)(wsf + o_ctl);
+  // bf16 handles: the backward's GEMMs run on the tensor cores like the
+  // forward's, on operands rounded to bf16 (the precision of every forward
+  // MMA operand: x, h, W) with fp32 accumulation.  fp32 handles, and
+  // RCU_ATTR_FORCE_PATH = 1, keep the fp32 FFMA GEMMs.  bf16 workspace,
+  // elements (every piece 256-byte aligned):
+  const bool tcg = h->dtype == RCU_BF16 && h->force_path != 1 && tc_gemm_supported(8, 8);
+  const int ldm8 = round_up(M, 8), g8 = round_up(G, 8), k8 = round_up(kmax, 8);
+  size_t boff = 0;
+  auto btake = [&](size_t n) { size_t r = boff; boff += (n + 127) & ~size_t(127); return r; };
+  const size_t b_x = btake(tcg ? (size_t)M * k8 : 0),        // x rows
+      b_hp = btake(tcg ? (size_t)M * ldo : 0),                  // h_{t-1} rows
+      b_whh = btake(tcg ? (size_t)G * ldo : 0),                 // W_hh rows
+      b_t1 = btake(tcg ? (size_t)G * ldm8 : 0),                 // DA^T
+      b_t2 = btake(tcg ? (size_t)kmax * ldm8 : 0),              // X^T
+      b_t3 = btake(tcg && cell == RCU_GRU ? (size_t)G * ldm8 : 0),  // DR^T
+      b_t4 = btake(tcg ? (size_t)Ho * ldm8 : 0),                // H_prev^T
+      b_da = btake(tcg ? (size_t)M * g8 : 0),                   // DA rows
+      b_wt = btake(tcg ? (size_t)kmax * g8 : 0);                // W_ih^T
+  if (tcg) CU(h->bwb.ensure(boff * 2));
+  __nv_bfloat16 *bws = (__nv_bfloat16 *)h->bwb.p;
+  auto aligned16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
   if ((int)h->gw.size() < L * D) h->gw.resize((size_t)L * D);
   h->grads_ready = false;
   int launches = 0;
@@ -1243,13 +1265,35 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
       CU(cudaMemcpyAsync(hp + (size_t)B * Ho, Y, (size_t)(T - 1) * B * Ho * 4,
                          cudaMemcpyDeviceToDevice, s));
     // pre-activations of every step
+    const bool tcr = tcg && tc_gemm_supported(K, G) && tc_gemm_supported(Ho, G);
+    int nl = 0;  // kernels launched by this (layer, direction)
     h->begin("bwd_recompute_gemm", s);
-    cudaError_t e = launch_gemm_simt<float, float>(X, K, Wih, ldk, (const float *)lw.bih_plain.p,
-                                                   zin, G, M, nullptr, G, K, s, err);
-    if (e == cudaSuccess)
-      e = launch_gemm_simt<float, float>(hp, Ho, (const float *)lw.whh_plain.p, ldo,
-                                         (const float *)lw.bhh_plain.p, zh, G, M, nullptr, G, Ho,
-                                         s, err);
+    cudaError_t e = cudaSuccess;
+    if (tcr) {
+      // the forward's own operands: bf16 x (or the previous layer's bf16
+      // output), bf16 h_{t-1}, the bf16 weights
+      __nv_bfloat16 *Xb = bws + b_x, *Hb = bws + b_hp, *Wb = bws + b_whh;
+      e = launch_convert_rows_bf16(X, M, K, K, Xb, ldk, s);
+      if (e == cudaSuccess)
+        e = launch_tc_gemm(Xb, ldk, (const __nv_bfloat16 *)h->wih[l].p + (size_t)d * G * ldk, ldk,
+                           (const float *)lw.bih_plain.p, zin, G, M, nullptr, G, K, h->nsm, s, err,
+                           (uint64_t)h->timeout_ns);
+      if (e == cudaSuccess) e = launch_convert_rows_bf16(hp, M, Ho, Ho, Hb, ldo, s);
+      if (e == cudaSuccess)
+        e = launch_convert_rows_bf16((const float *)lw.whh_plain.p, G, Ho, ldo, Wb, ldo, s);
+      if (e == cudaSuccess)
+        e = launch_tc_gemm(Hb, ldo, Wb, ldo, (const float *)lw.bhh_plain.p, zh, G, M, nullptr, G,
+                           Ho, h->nsm, s, err, (uint64_t)h->timeout_ns);
+      nl += 5;
+    } else {
+      e = launch_gemm_simt<float, float>(X, K, Wih, ldk, (const float *)lw.bih_plain.p, zin, G, M,
+                                         nullptr, G, K, s, err);
+      if (e == cudaSuccess)
+        e = launch_gemm_simt<float, float>(hp, Ho, (const float *)lw.whh_plain.p, ldo,
+                                           (const float *)lw.bhh_plain.p, zh, G, M, nullptr, G,
+                                           Ho, s, err);
+      nl += 2;
+    }
     h->end(s);
     const float *c0l = c0 ? c0 + (size_t)i * B * H : nullptr;
     h->begin("bwd_prep", s);
@@ -1318,31 +1362,66 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     }
     // weight gradients: dW_ih = DA^T X, dW_hh = DR^T H_prev (through transposes
     // to K-contiguous operands), db = column sums; input gradient dX = DA W_ih
+    const bool tw = tcg && (K % 4) == 0 && (Ho % 4) == 0 && (G % 4) == 0 && aligned16(gWih) &&
+                    aligned16(gWhh) && (!dX || aligned16(dX));
+    __nv_bfloat16 *T1b = bws + b_t1, *T2b = bws + b_t2, *T4b = bws + b_t4;
+    __nv_bfloat16 *T3b = cell == RCU_GRU ? bws + b_t3 : T1b;
     h->begin("bwd_transpose", s);
-    e = launch_transpose(DA, M, G, G, T1, M, s);
-    if (e == cudaSuccess) e = launch_transpose(X, M, K, K, T2, M, s);
-    if (e == cudaSuccess && cell == RCU_GRU) e = launch_transpose(DR, M, G, G, T3, M, s);
-    if (e == cudaSuccess) e = launch_transpose(hp, M, Ho, Ho, T4, M, s);
-    if (e == cudaSuccess) e = launch_transpose(Wih, G, K, ldk, WT, G, s);
+    if (tw) {
+      e = launch_transpose_bf16(DA, M, G, G, T1b, ldm8, s);
+      if (e == cudaSuccess) e = launch_transpose_bf16(X, M, K, K, T2b, ldm8, s);
+      if (e == cudaSuccess && cell == RCU_GRU) e = launch_transpose_bf16(DR, M, G, G, T3b, ldm8, s);
+      if (e == cudaSuccess) e = launch_transpose_bf16(hp, M, Ho, Ho, T4b, ldm8, s);
+      nl += cell == RCU_GRU ? 4 : 3;
+    } else {
+      e = launch_transpose(DA, M, G, G, T1, M, s);
+      if (e == cudaSuccess) e = launch_transpose(X, M, K, K, T2, M, s);
+      if (e == cudaSuccess && cell == RCU_GRU) e = launch_transpose(DR, M, G, G, T3, M, s);
+      if (e == cudaSuccess) e = launch_transpose(hp, M, Ho, Ho, T4, M, s);
+      if (e == cudaSuccess) e = launch_transpose(Wih, G, K, ldk, WT, G, s);
+      nl += cell == RCU_GRU ? 5 : 4;
+    }
     h->end(s);
     h->begin("bwd_weight_gemm", s);
-    if (e == cudaSuccess)
-      e = launch_gemm_simt<float, float>(T1, M, T2, M, nullptr, gWih, K, G, nullptr, K, M, s, err);
-    if (e == cudaSuccess)
-      e = launch_gemm_simt<float, float>(T3, M, T4, M, nullptr, gWhh, Ho, G, nullptr, Ho, M, s, err);
+    if (tw) {
+      if (e == cudaSuccess)
+        e = launch_tc_gemm(T1b, ldm8, T2b, ldm8, nullptr, gWih, K, G, nullptr, K, M, h->nsm, s,
+                           err, (uint64_t)h->timeout_ns);
+      if (e == cudaSuccess)
+        e = launch_tc_gemm(T3b, ldm8, T4b, ldm8, nullptr, gWhh, Ho, G, nullptr, Ho, M, h->nsm, s,
+                           err, (uint64_t)h->timeout_ns);
+    } else {
+      if (e == cudaSuccess)
+        e = launch_gemm_simt<float, float>(T1, M, T2, M, nullptr, gWih, K, G, nullptr, K, M, s, err);
+      if (e == cudaSuccess)
+        e = launch_gemm_simt<float, float>(T3, M, T4, M, nullptr, gWhh, Ho, G, nullptr, Ho, M, s, err);
+    }
+    nl += 2;
     h->end(s);
     h->begin("bwd_colsum", s);
     if (e == cudaSuccess) e = launch_colsum(DA, M, G, csum, gbih, s);
     if (e == cudaSuccess) e = launch_colsum(DR, M, G, csum, gbhh, s);
+    nl += 4;
     h->end(s);
     h->begin("bwd_dx_gemm", s);
-    if (e == cudaSuccess && dX)
-      e = launch_gemm_simt<float, float>(DA, G, WT, G, nullptr, dX, K, M, nullptr, K, G, s, err);
+    if (e == cudaSuccess && dX) {
+      if (tw) {
+        __nv_bfloat16 *DAb = bws + b_da, *WTb = bws + b_wt;
+        e = launch_convert_rows_bf16(DA, M, G, G, DAb, g8, s);
+        if (e == cudaSuccess) e = launch_transpose_bf16(Wih, G, K, ldk, WTb, g8, s);
+        if (e == cudaSuccess)
+          e = launch_tc_gemm(DAb, g8, WTb, g8, nullptr, dX, K, M, nullptr, K, G, h->nsm, s, err,
+                             (uint64_t)h->timeout_ns);
+        nl += 3;
+      } else {
+        e = launch_gemm_simt<float, float>(DA, G, WT, G, nullptr, dX, K, M, nullptr, K, G, s, err);
+        nl += 1;
+      }
+    }
     h->end(s);
     if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: gradients: %s", cudaGetErrorString(e));
-    // 5 GEMMs, 4 or 5 transposes, prep, recurrence, 2 two-kernel column sums;
-    // projection: 3 GEMMs, 4 transposes, up to 2 adds
-    launches += (cell == RCU_GRU ? 16 : 15) + (P > 0 ? 7 + (dhnl ? 1 : 0) + (T > 1 ? 1 : 0) : 0);
+    // plus prep and recurrence; projection: 3 GEMMs, 4 transposes, up to 2 adds
+    launches += nl + 2 + (P > 0 ? 7 + (dhnl ? 1 : 0) + (T > 1 ? 1 : 0) : 0);
     return RCU_OK;
   };
 

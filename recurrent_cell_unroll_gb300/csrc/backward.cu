@@ -295,9 +295,11 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
   }
 }
 
-// out[c][r] = in[r][c] for an R x C row-major matrix (ldi, ldo: row strides)
+// out[c][r] = in[r][c] for an R x C row-major matrix (ldi, ldo: row strides),
+// written as fp32 or rounded to bf16 (the tensor-core GEMM operand)
+template <typename OT>
 __global__ void transpose_kernel(const float *__restrict__ in, int R, int C, int ldi,
-                                 float *__restrict__ out, int ldo) {
+                                 OT *__restrict__ out, int ldo) {
   __shared__ float tile[32][33];
   const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
   for (int i = threadIdx.y; i < 32; i += 8) {
@@ -307,8 +309,16 @@ __global__ void transpose_kernel(const float *__restrict__ in, int R, int C, int
   __syncthreads();
   for (int i = threadIdx.y; i < 32; i += 8) {
     const int c = c0 + i, r = r0 + threadIdx.x;
-    if (r < R && c < C) out[(size_t)c * ldo + r] = tile[threadIdx.x][i];
+    if (r < R && c < C) out[(size_t)c * ldo + r] = Op<OT>::from_f(tile[threadIdx.x][i]);
   }
+}
+
+// out[r][c] = bf16(in[r][c]) for an R x C row-major matrix (row strides ldi, ldo)
+__global__ void convert_rows_kernel(const float *__restrict__ in, int R, int C, int ldi,
+                                    __nv_bfloat16 *__restrict__ out, int ldo) {
+  for (int r = blockIdx.x; r < R; r += gridDim.x)
+    for (int c = threadIdx.x; c < C; c += blockDim.x)
+      out[(size_t)r * ldo + c] = __float2bfloat16_rn(in[(size_t)r * ldi + c]);
 }
 
 // deterministic column sums of an M x N row-major matrix: chunk partials,
@@ -491,8 +501,23 @@ cudaError_t launch_bwd_rec(const BwdRecArgs &a, int nsm, cudaStream_t s) {
 cudaError_t launch_transpose(const float *in, int R, int C, int ldi, float *out, int ldo,
                              cudaStream_t s) {
   if (R <= 0 || C <= 0) return cudaSuccess;
-  transpose_kernel<<<dim3(ceil_div(C, 32), ceil_div(R, 32)), dim3(32, 8), 0, s>>>(in, R, C, ldi,
-                                                                                    out, ldo);
+  transpose_kernel<float><<<dim3(ceil_div(C, 32), ceil_div(R, 32)), dim3(32, 8), 0, s>>>(
+      in, R, C, ldi, out, ldo);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_bf16(const float *in, int R, int C, int ldi, __nv_bfloat16 *out,
+                                  int ldo, cudaStream_t s) {
+  if (R <= 0 || C <= 0) return cudaSuccess;
+  transpose_kernel<__nv_bfloat16><<<dim3(ceil_div(C, 32), ceil_div(R, 32)), dim3(32, 8), 0, s>>>(
+      in, R, C, ldi, out, ldo);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_convert_rows_bf16(const float *in, int R, int C, int ldi, __nv_bfloat16 *out,
+                                     int ldo, cudaStream_t s) {
+  if (R <= 0 || C <= 0) return cudaSuccess;
+  convert_rows_kernel<<<std::min(R, 65535), 256, 0, s>>>(in, R, C, ldi, out, ldo);
   return cudaGetLastError();
 }
 

@@ -219,6 +219,12 @@ int bwd_units_per_cta(int H, int B, int nG, int nsm);
 cudaError_t launch_bwd_rec(const BwdRecArgs &a, int nsm, cudaStream_t s);
 cudaError_t launch_transpose(const float *in, int R, int C, int ldi, float *out, int ldo,
                              cudaStream_t s);
+// the same, rounded to bf16 (a tensor-core GEMM operand), and a row-wise
+// fp32 -> bf16 copy with its own row strides
+cudaError_t launch_transpose_bf16(const float *in, int R, int C, int ldi, __nv_bfloat16 *out,
+                                  int ldo, cudaStream_t s);
+cudaError_t launch_convert_rows_bf16(const float *in, int R, int C, int ldi, __nv_bfloat16 *out,
+                                     int ldo, cudaStream_t s);
 size_t colsum_scratch_floats(int M, int N);
 cudaError_t launch_colsum(const float *A, int M, int N, float *scratch, float *out,
                           cudaStream_t s);

@@ -117,15 +117,23 @@ BWD_BF16_SPECS = [
     # the 3-layer GRU workload's width: 1024 units, 256 rows (the reverse-time
     # kernel's plan shrinks its K slices to fit), short T, one layer
     wl.GRU_3L.scaled(T=3, B=256, in_dim=64, hidden=1024, layers=1, h0_std=0.1),
+    # T*B = 185 rows (not a multiple of 8) and an input width that is not
+    # either: the bf16 operand copies are padded row by row
+    wl.GRU_3L.scaled(T=5, B=37, in_dim=60, hidden=96, layers=2, h0_std=0.5),
+    # input width 13: the weight-gradient GEMMs keep the fp32 path (their
+    # output rows need a multiple of 4), the recompute runs on the tensor cores
+    wl.LSTM_T80.scaled(T=6, B=20, in_dim=13, hidden=48, dtype="bf16", h0_std=0.5, c0_std=0.5),
 ]
 
 
 @pytest.mark.parametrize("spec", BWD_BF16_SPECS, ids=_bwd_id)
 def test_backward_bf16_parity(spec):
-    """bf16 handles: the fp32 gradient of the model with the bf16-rounded
-    weights the forward used, against the oracle with the same rounded
-    weights (bf16 tier: relative 2e-2; the forward's bf16 activation
-    rounding is in the recomputed states)."""
+    """bf16 handles: the gradient of the model with the bf16-rounded weights
+    the forward used, its GEMMs on the tensor cores (operands rounded to bf16
+    as the forward's are, fp32 accumulation), against the oracle's fp64
+    gradient of the model with the same rounded weights (bf16 tier: relative
+    2e-2; the forward's bf16 activation rounding is in the recomputed
+    states)."""
     inp = wl.make_rnn_inputs(spec, seed=13)
     g = torch.Generator().manual_seed(98)
     L, B, Ho = spec.layers, spec.B, spec.Hout
