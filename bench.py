@@ -448,7 +448,6 @@ TRAFFIC = {
     ("lstm_train_f32_T500_B64_256x512", "bwd_recurrent"): 630.8e6,
     ("bilstm_train_f32_varlen_B64_T500_256x512", "bwd_recurrent"): 456.0e6,
     ("rssm_train_f32_B50_T50_S20_A6_H200", "rssm_bwd_chain"): 18.8e6,
-    ("gru_train_bf16_3L_T512_B256_1024", "bwd_recurrent"): 6437.2e6,
 }
 
 
@@ -503,7 +502,8 @@ def _roofline(spec, inp, prof, peaks, nsm, step_ms=None, region_s=None, steps=1)
     name, (ms, n) = max(prof.items(), key=lambda kv: kv[1][0])
     fl = kernel_flops(spec, inp)
     kind = name if name in fl else "recurrent" if name.startswith("recurrent") else (
-        "input_gemm" if name.startswith("input_gemm") else None)
+        "input_gemm" if name.startswith("input_gemm") else
+        "bwd_recurrent" if name.startswith("bwd_recurrent") else None)
     if kind is None:
         return None
     # the kind's FLOPs of all timed steps over its launches (one launch per

@@ -1181,7 +1181,8 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
                o_dym = take(lengths ? TBO : 0),
                // cell clipping: the unclamped cell state of every step
                o_cr = take(cell == RCU_LSTM && h->cclip ? TBH : 0),
-               o_xm = take(lengths ? (size_t)M * h->in_l[0] : 0), o_ctl = take(64);
+               o_xm = take(lengths ? (size_t)M * h->in_l[0] : 0),
+               o_ctl = take((size_t)std::max(64, tc_bwd_counters(B)));
   CU(h->bw.ensure(off * 4));
   float *wsf = (float *)h->bw.p;
   float *keep = wsf + o_keep, *hp = wsf + o_hp, *zin = wsf + o_zin, *zh = wsf + o_zh;
@@ -1214,7 +1215,9 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
       b_t3 = btake(tcg && cell == RCU_GRU ? (size_t)G * ldm8 : 0),  // DR^T
       b_t4 = btake(tcg ? (size_t)Ho * ldm8 : 0),                // H_prev^T
       b_da = btake(tcg ? (size_t)M * g8 : 0),                   // DA rows
-      b_wt = btake(tcg ? (size_t)kmax * g8 : 0);                // W_ih^T
+      b_wt = btake(tcg ? (size_t)kmax * g8 : 0),                // W_ih^T
+      b_wth = btake(tcg && cell == RCU_GRU ? (size_t)H * g8 : 0),        // W_hh^T
+      b_xdr = btake(tcg && cell == RCU_GRU ? 2 * (size_t)B * g8 : 0);    // dR_t exchange
   if (tcg) CU(h->bwb.ensure(boff * 2));
   __nv_bfloat16 *bws = (__nv_bfloat16 *)h->bwb.p;
   auto aligned16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
@@ -1320,8 +1323,29 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
       rec_W = Fw;
       rec_ldw = ldh;
     }
-    // the reverse-time recurrence
-    CU(cudaMemsetAsync(ctr, 0, 16 * 4, s));
+    // the reverse-time recurrence: on the tensor cores for the GRU of a bf16
+    // handle over fixed-length rows (W_hh^T dR_{t+1} with bf16 operands, as
+    // every MMA of its forward), else the FFMA kernel
+    CU(cudaMemsetAsync(ctr, 0, (size_t)std::max(64, tc_bwd_counters(B)) * 4, s));
+    const bool tcb = tcg && cell == RCU_GRU && P == 0 && !lengths && tc_bwd_supported(H, B, h->nsm);
+    if (tcb) {
+      __nv_bfloat16 *WTh = bws + b_wth, *XDR = bws + b_xdr;
+      h->begin("bwd_recurrent_tc", s);
+      e = launch_transpose_bf16((const float *)lw.whh_plain.p, G, H, ldo, WTh, g8, s);
+      TcBwdParams q{};
+      q.T = T; q.B = B; q.H = H;
+      q.gates = zin; q.zh = zh; q.hp = hp; q.dy = rec_dy;
+      q.dhn = dhnl;
+      q.DA = DA; q.DR = DR;
+      q.dh0 = dh0 ? dh0 + (size_t)i * B * H : nullptr;
+      q.xdr = XDR; q.Kx = g8; q.wt = WTh;
+      q.ctr = ctr; q.err = err; q.timeout_ns = (uint64_t)h->timeout_ns;
+      q.drop_arrival = h->drop_arrival == 2 && l == L - 1 && d == 0;
+      if (e == cudaSuccess) e = launch_tc_bwd(q, h->nsm, s);
+      h->end(s);
+      if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: recurrence: %s", cudaGetErrorString(e));
+      nl += 2;
+    }
     BwdRecArgs a{};
     a.T = T; a.B = B; a.H = H; a.cell = cell;
     a.Whh = rec_W; a.ldw = rec_ldw;
@@ -1335,10 +1359,13 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     a.dc0 = dc0 ? dc0 + (size_t)i * B * H : nullptr;
     a.ctr = ctr; a.err = err; a.timeout_ns = (uint64_t)h->timeout_ns;
     a.drop_arrival = h->drop_arrival == 2 && l == L - 1 && d == 0;
-    h->begin("bwd_recurrent", s);
-    e = launch_bwd_rec(a, h->nsm, s);
-    h->end(s);
-    if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: recurrence: %s", cudaGetErrorString(e));
+    if (!tcb) {
+      h->begin("bwd_recurrent", s);
+      e = launch_bwd_rec(a, h->nsm, s);
+      h->end(s);
+      if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: recurrence: %s", cudaGetErrorString(e));
+      nl += 1;
+    }
     DevBuf &g = h->gw[(size_t)i];
     CU(g.ensure(((size_t)G * K + (size_t)G * Ho + 2 * (size_t)G + (size_t)P * H) * 4));
     float *gWih = (float *)g.p, *gWhh = gWih + (size_t)G * K, *gbih = gWhh + (size_t)G * Ho,
@@ -1420,8 +1447,8 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     }
     h->end(s);
     if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: gradients: %s", cudaGetErrorString(e));
-    // plus prep and recurrence; projection: 3 GEMMs, 4 transposes, up to 2 adds
-    launches += nl + 2 + (P > 0 ? 7 + (dhnl ? 1 : 0) + (T > 1 ? 1 : 0) : 0);
+    // plus prep; projection: 3 GEMMs, 4 transposes, up to 2 adds
+    launches += nl + 1 + (P > 0 ? 7 + (dhnl ? 1 : 0) + (T > 1 ? 1 : 0) : 0);
     return RCU_OK;
   };
 

@@ -761,6 +761,11 @@ bool make_map(CUtensorMap *map, const void *base, long long rows, int cols, int 
 
 }  // namespace
 
+bool tc_map_2d(CUtensorMap *map, const void *base, long long rows, int cols, int ld,
+               int box_rows) {
+  return make_map(map, base, rows, cols, ld, box_rows);
+}
+
 int tc_rec_units() { return UNITS; }
 
 bool tc_rec_packable(int cell, int H, int Hout, int P) {
@@ -826,10 +831,17 @@ bool ks_fits(int nG, int K, int ks) {
 // cannot be resident at once.
 bool launch_clustered(const void *fn, int grid, int cs, size_t smem, void **args, cudaStream_t s,
                       cudaError_t *err) {
+  return tc_launch_clustered(fn, grid, NT, cs, smem, args, s, err);
+}
+
+}  // namespace
+
+bool tc_launch_clustered(const void *fn, int grid, int nthreads, int cs, size_t smem, void **args,
+                         cudaStream_t s, cudaError_t *err) {
   *err = cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(NT);
+  cfg.blockDim = dim3(nthreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   int max_clusters = 0;
@@ -846,8 +858,6 @@ bool launch_clustered(const void *fn, int grid, int cs, size_t smem, void **args
   *err = cudaLaunchKernelExC(&cfg, fn, args);
   return true;
 }
-
-}  // namespace
 
 cudaError_t launch_tc_recurrent(const TcRecParams &tp, int nsm, cudaStream_t s) {
   (void)nsm;

@@ -7,6 +7,8 @@
 
 #include <vector>
 
+#include <cuda.h>
+
 #include "internal.h"
 
 namespace rcu {
@@ -37,5 +39,41 @@ int tc_rec_grid(int cell, int H, int Hout, int B, int D, int ksplit);
 void tc_pack_whh(int cell, int H, int Hout, const float *whh, std::vector<uint16_t> &out,
                  uint16_t (*to_bf16)(float));
 cudaError_t launch_tc_recurrent(const TcRecParams &p, int nsm, cudaStream_t s);
+
+// Shared host helpers of the tcgen05 kernels: a 2D bf16 tensor map with
+// 128-byte swizzle (box 64 columns x box_rows rows; row stride ld elements,
+// a multiple of 8), and a cooperative launch of `grid` CTAs of a kernel that
+// declares its own cluster shape of `cs` CTAs (false, nothing launched, when
+// that cluster grid cannot be resident at once).
+bool tc_map_2d(CUtensorMap *map, const void *base, long long rows, int cols, int ld, int box_rows);
+bool tc_launch_clustered(const void *fn, int grid, int nthreads, int cs, size_t smem, void **args,
+                         cudaStream_t s, cudaError_t *err);
+
+// ---- bwd_tc.cu: the reverse-time recurrence of the GRU backward pass with
+// the per-step W_hh^T dR_t on tcgen05 (bf16 handles, fixed-length batches).
+// Per reverse step t it forms dh_t = dy_t + z_{t+1} dh_{t+1} + W_hh^T dR_{t+1}
+// (dh_{T-1} = dy_{T-1} + dh_n), the gate gradients of step t (DA: input side,
+// DR: hidden side, fp32, every row), publishes dR_t as the next step's bf16
+// MMA operand, and finally dh0 = z_0 dh_0 + W_hh^T dR_0.
+struct TcBwdParams {
+  int T, B, H;
+  const float *gates;  // [T*B][3H]: activated r, z, n
+  const float *zh;     // [T*B][3H]: hidden-side pre-activations (n part: W_hn h' + b_hn)
+  const float *hp;     // [T*B][H]: h_{t-1}
+  const float *dy;     // [T*B][H]
+  const float *dhn;    // [B][H] or NULL
+  float *DA, *DR;      // [T*B][3H]
+  float *dh0;          // [B][H] or NULL
+  __nv_bfloat16 *xdr;  // [2][B][Kx]: dR_t exchange, bf16 (buffer t & 1)
+  int Kx;              // its row stride (a multiple of 8, >= 3H)
+  const __nv_bfloat16 *wt;  // [H][Kx]: W_hh^T, bf16
+  unsigned *ctr;       // step counters (tc_bwd_counters words, zeroed)
+  int *err;
+  uint64_t timeout_ns;
+  int drop_arrival;
+};
+bool tc_bwd_supported(int H, int B, int nsm);
+int tc_bwd_counters(int B);
+cudaError_t launch_tc_bwd(const TcBwdParams &p, int nsm, cudaStream_t s);
 
 }  // namespace rcu

@@ -170,7 +170,7 @@ def test_traffic_table_names_real_workloads_and_kernels():
     name the roofline can report for it."""
     names = {s.name for s in bench.WORKLOADS.values()}
     kinds = {"recurrent_tc", "recurrent_tc_lstmp", "recurrent_simt", "recurrent_cluster",
-             "rssm_unroll", "bwd_recurrent", "rssm_bwd_chain"}
+             "rssm_unroll", "bwd_recurrent", "bwd_recurrent_tc", "rssm_bwd_chain"}
     for (workload, kernel), traffic in bench.TRAFFIC.items():
         assert workload in names, workload
         assert kernel in kinds, kernel
@@ -239,3 +239,21 @@ def test_oracle_sample_prefix_and_plan():
     rs = wl.RSSM_TRAIN.scaled(T=9, B=3)
     sp, ip = bench.prefix(rs, wl.make_rssm_inputs(rs, seed=2), 4)
     assert sp.T == 4 and ip["eps"].shape[0] == 4 and ip["dbeliefs"].shape[0] == 4
+
+
+def test_roofline_bound_follows_the_kernel():
+    """A tcgen05 kernel is held to the tensor peak, an FFMA kernel to the FP32
+    ALU peak, whatever the handle's dtype; the tcgen05 reverse-time kernel
+    counts the reverse-time recurrence's FLOPs."""
+    spec = wl.GRU_TRAIN.scaled(T=4, B=8, in_dim=16, hidden=32)
+    inp = wl.make_rnn_inputs(spec, seed=0)
+    peaks = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2000.0,
+             "source": "test"}
+    fl = bench.kernel_flops(spec, inp)
+    tc = bench._roofline(spec, inp, {"bwd_recurrent_tc": (2.0, 2), "bwd_prep": (1.0, 2)},
+                         peaks, 148, region_s=0.1, steps=2)
+    assert tc["bound"] == "tensor" and tc["peak"] == 1900.0
+    assert tc["algorithmic_flop_per_launch"] == sum(fl["bwd_recurrent"])
+    ffma = bench._roofline(spec, inp, {"bwd_recurrent": (2.0, 2)}, peaks, 148, region_s=0.1,
+                           steps=2)
+    assert ffma["bound"] == "alu" and ffma["peak"] == round(bench.fp32_alu_peak_tflops(148, 2000.0), 1)

@@ -141,6 +141,7 @@ def test_backward_bf16_parity(spec):
     dev = torch.device("cuda")
     net = binding.RNN.from_spec(spec)
     net.set_weights(inp["weights"])
+    net.set_attr(binding.RCU_ATTR_PROFILE, 1)
 
     def d(t):
         return None if t is None else t.to(dev)
@@ -148,6 +149,10 @@ def test_backward_bf16_parity(spec):
                                        h0=d(inp["h0"]), c0=d(inp["c0"]))
     torch.cuda.synchronize()
     assert net.status() == 0
+    # the GRU over fixed-length rows (widths of whole 32-unit clusters) takes
+    # the tcgen05 reverse-time kernel, every other form the FFMA one
+    tc_rec = spec.cell == "gru" and spec.varlen is None and spec.hidden % 32 == 0
+    assert ("bwd_recurrent_tc" in net.profile()) == tc_rec, net.profile()
     ref = oracle.rnn_backward(_cell(spec), inp["x"], inp["weights"], dy, hidden=spec.hidden,
                               proj=spec.proj, lengths=inp["lengths"], h0=inp["h0"],
                               c0=inp["c0"], bf16_weights=True)
