@@ -415,3 +415,31 @@ def test_training_pass_full_size(spec):
         print(f"{name}: rel {e:.2e}")
         assert e <= BWD_REL, f"{name}: relative max error {e:.3e}"
     net.close()
+
+
+def test_gru_training_full_width_sampled_rows():
+    """The 3-layer GRU training workload's width and batch (1024 units, 256
+    rows: two batch groups on the 4-CTA tcgen05 reverse-time kernel) over 16
+    steps.  Rows are independent in dx and dh0, so 6 rows spread over both
+    batch groups and the TMEM lane quarters are checked against the oracle run
+    on those rows alone (the weight gradients, sums over every row, are
+    checked at this width over all rows by test_backward_bf16_parity)."""
+    spec = wl.GRU_TRAIN.scaled(T=16)
+    inp = wl.make_rnn_inputs(spec, seed=0)
+    dev = torch.device("cuda")
+    net = binding.RNN.from_spec(spec)
+    net.set_weights(inp["weights"])
+    net.set_attr(binding.RCU_ATTR_PROFILE, 1)
+    d = lambda t: None if t is None else t.to(dev)
+    dx, dh0, _, _ = net.backward(d(inp["x"]), d(inp["dy"]), h0=d(inp["h0"]))
+    torch.cuda.synchronize()
+    assert net.status() == 0
+    assert "bwd_recurrent_tc" in net.profile(), net.profile()
+    rows = [0, 31, 32, 127, 128, 255]
+    ref = oracle.rnn_backward(oracle.GRU, inp["x"][:, rows], inp["weights"], inp["dy"][:, rows],
+                              hidden=spec.hidden, h0=inp["h0"][:, rows], bf16_weights=True)
+    for name, got, want in (("dx", dx[:, rows], ref["dx"]), ("dh0", dh0[:, rows], ref["dh0"])):
+        e = _rel(got.cpu().numpy().astype(np.float64), want)
+        print(f"{name}: rel {e:.2e}")
+        assert e <= BF16_REL, f"{name}: relative max error {e:.3e}"
+    net.close()
