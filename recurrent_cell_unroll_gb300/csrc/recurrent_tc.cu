@@ -45,15 +45,16 @@ struct Maps {
   CUtensorMap hx;    // [D*2*B rows][K cols], ld Kp, bf16, box 64 x a_rows
   CUtensorMap w[2];  // per direction [NU16*nG*16 rows][K cols], ld Kp, bf16, box 64 x N
   // Tiled input and output streams (fixed-length batches: a step's rows are
-  // contiguous): G as [T][B][ldG] fp32 and the layer output as [T][B][ldo]
-  // (fp32 y, or bf16 packed rows for the next layer), boxes of 16 bytes of
-  // columns (4 fp32 or 8 bf16) x a_rows rows x 1 step, so that in shared
-  // memory each box is a strip of 16-byte rows: a warp's 32 rows of one
-  // strip are 512 contiguous bytes (no bank conflicts).  Rows past B fall
+  // contiguous): G as [T][B][ldG] fp32 and the layer outputs as [T][B][ldo]
+  // (fp32 y and / or the bf16 packed rows for the next layer), boxes of 16
+  // bytes of columns (4 fp32 or 8 bf16) x a_rows rows x 1 step, so that in
+  // shared memory each box is a strip of 16-byte rows: a warp's 32 rows of
+  // one strip are 512 contiguous bytes (no bank conflicts).  Rows past B fall
   // outside the box's step and are clipped (stores) or read as zero (loads).
-  CUtensorMap g, out;
-  int tiles;         // 1: G and the output move through these maps
-  int out_bf16;      // the output map is the bf16 one
+  CUtensorMap g, out, outm;
+  // 0: no tiles; else G moves through `g`, and bit 0 / bit 1 say that fp32 y
+  // (`out`) / the bf16 rows (`outm`) move through their maps
+  int tiles;
   // h rows loaded per stage: 128, or round_up(B, 8) when one batch group
   // holds the whole batch (the stage's other rows are never read back: a
   // row of D depends only on the same row of A, and the epilogue skips rows
@@ -84,9 +85,10 @@ struct Geo {
   size_t w_bytes, x_bytes, g_bytes, o_bytes, smem;
 };
 
-// tiles: reserve the G tile [nG][128 rows][16 units] fp32 and the output
-// tile [128 rows][16 units] (fp32 room) of the tiled streams
-__host__ __device__ inline Geo make_geo(int nG, int K, int KS, bool tiles = false) {
+// tiles (the Maps::tiles mask): reserve the G tile [nG][128 rows][16 units]
+// fp32 and the output tiles [128 rows][16 units] of the tiled streams (fp32
+// y: 8 KB, bf16 rows: 4 KB)
+__host__ __device__ inline Geo make_geo(int nG, int K, int KS, int tiles = 0) {
   Geo g;
   g.N = nG * UNITS * KS;
   g.nkb = ceil_div(K, BK);
@@ -95,7 +97,7 @@ __host__ __device__ inline Geo make_geo(int nG, int K, int KS, bool tiles = fals
   // partial sums received from the other KS-1 CTAs: [KS-1][nG][4][128] float4
   g.x_bytes = (size_t)(KS - 1) * nG * 4 * BG * 16;
   g.g_bytes = tiles ? (size_t)nG * BG * UNITS * 4 : 0;
-  g.o_bytes = tiles ? (size_t)BG * UNITS * 4 : 0;
+  g.o_bytes = (size_t)((tiles & 1) ? BG * UNITS * 4 : 0) + ((tiles & 2) ? BG * UNITS * 2 : 0);
   const size_t fixed = 1024 + g.w_bytes + g.x_bytes + g.g_bytes + g.o_bytes + 256;
   int st = (int)((SMEM_LIMIT - (long long)fixed) / A_STAGE);
   g.stages = st > MAX_STAGES ? MAX_STAGES : st;
@@ -178,13 +180,14 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
-  const Geo geo = make_geo(NG, p.Hout, KS, maps.tiles != 0);
+  const Geo geo = make_geo(NG, p.Hout, KS, maps.tiles);
   const int N = geo.N, STG = geo.stages;
   uint8_t *sW = smem;                       // resident B operand, nkbm blocks of N x 128 B
   uint8_t *sA = smem + geo.w_bytes;         // ring of STG stages of 128 x 128 B
   float4 *xbuf = reinterpret_cast<float4 *>(sA + (size_t)STG * A_STAGE);
   float *gtile = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(xbuf) + geo.x_bytes);
-  uint8_t *otile = reinterpret_cast<uint8_t *>(gtile) + geo.g_bytes;
+  uint8_t *otile = reinterpret_cast<uint8_t *>(gtile) + geo.g_bytes;  // fp32 y strips, then
+  uint8_t *otile_m = otile + ((maps.tiles & 1) ? BG * UNITS * 4 : 0);   // the bf16 strips
   Ctl *ctl = reinterpret_cast<Ctl *>(otile + geo.o_bytes);
 
   const int NU = p.NU, NBG = ceil_div(p.B, BG);  // NU = CTAs per (direction, batch group)
@@ -573,18 +576,18 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
       }
       if (tiles && row_ok) {
         // the layer output of this row and units, for one TMA store per step
-        if (maps.out_bf16) {
+        if (maps.tiles & 2) {
           __nv_bfloat162 lo = __floats2bfloat162_rn(h[0], h[1]);
           __nv_bfloat162 hi = __floats2bfloat162_rn(h[2], h[3]);
           uint2 pk;
           pk.x = *reinterpret_cast<uint32_t *>(&lo);
           pk.y = *reinterpret_cast<uint32_t *>(&hi);
           // bf16 strips of 8 units (16-byte rows): part pairs share one
-          *reinterpret_cast<uint2 *>(otile + (((size_t)(part >> 1) * BG + r) * 2 * UPT + (part & 1) * UPT) * 2) = pk;
-        } else {
+          *reinterpret_cast<uint2 *>(otile_m + (((size_t)(part >> 1) * BG + r) * 2 * UPT + (part & 1) * UPT) * 2) = pk;
+        }
+        if (maps.tiles & 1)
           *reinterpret_cast<float4 *>(otile + ((size_t)part * BG + r) * UPT * 4) =
               make_float4(h[0], h[1], h[2], h[3]);
-        }
         fence_proxy_async_shared();
       }
       if (p.trace && threadIdx.x == 64) stamp(p, step, 6, globaltimer_ns());
@@ -601,10 +604,15 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
           // step's G tile (every thread read this step's above)
           if (u0 < p.Hout) {
             // one store per strip: 4 fp32 or 8 bf16 units of every row
-            const int su = maps.out_bf16 ? 2 * UPT : UPT, ns = UNITS / su;
-            for (int q4 = 0; q4 < ns; ++q4)
-              tma_store_3d(&maps.out, otile + (size_t)q4 * BG * su * (maps.out_bf16 ? 2 : 4),
-                           d * p.Hout + u0 + q4 * su, row0, d == 0 ? step : Tg - 1 - step);
+            const int ts = d == 0 ? step : Tg - 1 - step;
+            if (maps.tiles & 1)
+              for (int q4 = 0; q4 < UNITS / UPT; ++q4)
+                tma_store_3d(&maps.out, otile + (size_t)q4 * BG * UPT * 4,
+                             d * p.Hout + u0 + q4 * UPT, row0, ts);
+            if (maps.tiles & 2)
+              for (int q8 = 0; q8 < UNITS / (2 * UPT); ++q8)
+                tma_store_3d(&maps.outm, otile_m + (size_t)q8 * BG * 2 * UPT * 2,
+                             d * p.Hout + u0 + q8 * 2 * UPT, row0, ts);
           }
           if (step + 1 < Tg) issue_g(step + 1);
         }
@@ -878,25 +886,25 @@ cudaError_t launch_tc_recurrent(const TcRecParams &tp, int nsm, cudaStream_t s) 
   while (ks > 1 && !ks_fits(nG, p.Hout, ks)) ks /= 2;
 
   // Tiled G and output streams: fixed-length batches (a step's rows are
-  // contiguous), one output (y, or the bf16 rows of the next layer), 16-byte
-  // aligned rows and bases, whole 16-unit tiles of the output, and a ring of
+  // contiguous), 16-byte aligned rows and bases, whole 16-unit tiles of the
+  // outputs (fp32 y and / or the bf16 rows of the next layer), and a ring of
   // at least 4 h stages beside the tiles
   const bool y_out = p.y != nullptr, m_out = p.ymid != nullptr;
   const int ldo = p.D * p.Hout;
   auto aligned16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
-  const bool tiles_ok = tp.fixed_length && (y_out != m_out) && (p.H % 4) == 0 &&
+  const bool tiles_ok = tp.fixed_length && (y_out || m_out) && (p.H % 4) == 0 &&
                         (p.Hout % UNITS) == 0 && ((size_t)p.ldG * 4) % 16 == 0 &&
-                        ((size_t)ldo * (y_out ? 4 : 2)) % 16 == 0 && aligned16(p.G) &&
-                        aligned16(y_out ? (const void *)p.y : p.ymid);
+                        ((size_t)ldo * 2) % 16 == 0 && aligned16(p.G) &&
+                        (!y_out || aligned16(p.y)) && (!m_out || aligned16(p.ymid));
+  const int tmask = (y_out ? 1 : 0) | (m_out ? 2 : 0);
 
   for (int attempt = 0; attempt < 3; ++attempt) {
-    maps.tiles = tiles_ok && make_geo(nG, p.Hout, ks, true).stages >= 4 ? 1 : 0;
-    const Geo geo = make_geo(nG, p.Hout, ks, maps.tiles != 0);
-    maps.out_bf16 = m_out ? 1 : 0;
+    maps.tiles = tiles_ok && make_geo(nG, p.Hout, ks, tmask).stages >= 4 ? tmask : 0;
+    const Geo geo = make_geo(nG, p.Hout, ks, maps.tiles);
     if (maps.tiles &&
         (!make_map_steps(&maps.g, p.G, false, p.T, p.B, p.ldG, p.ldG, maps.a_rows) ||
-         !make_map_steps(&maps.out, y_out ? (const void *)p.y : p.ymid, m_out, p.T, p.B, ldo, ldo,
-                         maps.a_rows)))
+         (y_out && !make_map_steps(&maps.out, p.y, false, p.T, p.B, ldo, ldo, maps.a_rows)) ||
+         (m_out && !make_map_steps(&maps.outm, p.ymid, true, p.T, p.B, ldo, ldo, maps.a_rows))))
       return cudaErrorInvalidValue;
     p.NU = ks > 1 ? ks * ceil_div(p.H, ks * UNITS) : NU16;
     for (int d = 0; d < 2; ++d) {
