@@ -449,7 +449,6 @@ TRAFFIC = {
     ("lstm_train_f32_T500_B64_256x512", "bwd_recurrent"): 630.8e6,
     ("bilstm_train_f32_varlen_B64_T500_256x512", "bwd_recurrent"): 456.0e6,
     ("rssm_train_f32_B50_T50_S20_A6_H200", "rssm_bwd_chain"): 18.8e6,
-    ("gru_train_bf16_3L_T512_B256_1024", "bwd_recurrent_tc"): 6489.0e6,
 }
 
 

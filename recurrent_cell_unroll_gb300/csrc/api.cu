@@ -1182,6 +1182,8 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
                // cell clipping: the unclamped cell state of every step
                o_cr = take(cell == RCU_LSTM && h->cclip ? TBH : 0),
                o_xm = take(lengths ? (size_t)M * h->in_l[0] : 0),
+               // the tcgen05 GRU reverse-time kernel's bias sums [2][batch groups][G]
+               o_bs = take(h->dtype == RCU_BF16 && cell == RCU_GRU ? 2 * (size_t)ceil_div(B, 128) * G : 0),
                o_ctl = take((size_t)std::max(64, tc_bwd_counters(B)));
   CU(h->bw.ensure(off * 4));
   float *wsf = (float *)h->bw.p;
@@ -1197,6 +1199,7 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
   float *XR = wsf + o_xr, *YD = wsf + o_yd, *DYD = wsf + o_dyd, *DXR = wsf + o_dxr,
         *TMP = wsf + o_tmp, *DYM = wsf + o_dym, *XM = wsf + o_xm;
   float *CR = (cell == RCU_LSTM && h->cclip) ? wsf + o_cr : nullptr;
+  float *BS = wsf + o_bs;
   unsigned *ctr = (unsigned *)(wsf + o_ctl);
   // bf16 handles: the backward's GEMMs run on the tensor cores like the
   // forward's, on operands rounded to bf16 (the precision of every forward
@@ -1327,7 +1330,21 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     // handle over fixed-length rows (W_hh^T dR_{t+1} with bf16 operands, as
     // every MMA of its forward), else the FFMA kernel
     CU(cudaMemsetAsync(ctr, 0, (size_t)std::max(64, tc_bwd_counters(B)) * 4, s));
+    DevBuf &g = h->gw[(size_t)i];
+    CU(g.ensure(((size_t)G * K + (size_t)G * Ho + 2 * (size_t)G + (size_t)P * H) * 4));
+    float *gWih = (float *)g.p, *gWhh = gWih + (size_t)G * K, *gbih = gWhh + (size_t)G * Ho,
+          *gbhh = gbih + G, *gWhr = gbhh + G;
+    // the weight and input gradients on the tensor cores (below)
+    const bool tw = tcg && (K % 4) == 0 && (Ho % 4) == 0 && (G % 4) == 0 && aligned16(gWih) &&
+                    aligned16(gWhh) && (!dX || aligned16(dX));
     const bool tcb = tcg && cell == RCU_GRU && P == 0 && !lengths && tc_bwd_supported(H, B, h->nsm);
+    // with both, the reverse-time kernel writes the gate gradients straight
+    // in the forms those GEMMs read (DA^T, DR^T and DA in bf16, the bias sums
+    // per batch group): no fp32 DA / DR, transposes or column sums of them
+    const bool tcd = tcb && tw;
+    __nv_bfloat16 *T1b = bws + b_t1, *T2b = bws + b_t2, *T4b = bws + b_t4;
+    __nv_bfloat16 *T3b = cell == RCU_GRU ? bws + b_t3 : T1b, *DAb = bws + b_da;
+    const int nbg = ceil_div(B, 128);
     if (tcb) {
       __nv_bfloat16 *WTh = bws + b_wth, *XDR = bws + b_xdr;
       h->begin("bwd_recurrent_tc", s);
@@ -1336,7 +1353,13 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
       q.T = T; q.B = B; q.H = H;
       q.gates = zin; q.zh = zh; q.hp = hp; q.dy = rec_dy;
       q.dhn = dhnl;
-      q.DA = DA; q.DR = DR;
+      if (tcd) {
+        q.dat = T1b; q.drt = T3b; q.ldt = ldm8;
+        q.dab = dX ? DAb : nullptr; q.ldab = g8;
+        q.bsum = BS;
+      } else {
+        q.DA = DA; q.DR = DR;
+      }
       q.dh0 = dh0 ? dh0 + (size_t)i * B * H : nullptr;
       q.xdr = XDR; q.Kx = g8; q.wt = WTh;
       q.ctr = ctr; q.err = err; q.timeout_ns = (uint64_t)h->timeout_ns;
@@ -1366,10 +1389,6 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
       if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: recurrence: %s", cudaGetErrorString(e));
       nl += 1;
     }
-    DevBuf &g = h->gw[(size_t)i];
-    CU(g.ensure(((size_t)G * K + (size_t)G * Ho + 2 * (size_t)G + (size_t)P * H) * 4));
-    float *gWih = (float *)g.p, *gWhh = gWih + (size_t)G * K, *gbih = gWhh + (size_t)G * Ho,
-          *gbhh = gbih + G, *gWhr = gbhh + G;
     // projection: R = DZ W_hh (R_t = W_hh^T dz_t), dh0 = R_0, dh_t = dy'_t + R_{t+1},
     // dW_hr = sum_t dh_t m_t^T
     if (P > 0) {
@@ -1389,12 +1408,12 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     }
     // weight gradients: dW_ih = DA^T X, dW_hh = DR^T H_prev (through transposes
     // to K-contiguous operands), db = column sums; input gradient dX = DA W_ih
-    const bool tw = tcg && (K % 4) == 0 && (Ho % 4) == 0 && (G % 4) == 0 && aligned16(gWih) &&
-                    aligned16(gWhh) && (!dX || aligned16(dX));
-    __nv_bfloat16 *T1b = bws + b_t1, *T2b = bws + b_t2, *T4b = bws + b_t4;
-    __nv_bfloat16 *T3b = cell == RCU_GRU ? bws + b_t3 : T1b;
     h->begin("bwd_transpose", s);
-    if (tw) {
+    if (tcd) {
+      e = launch_transpose_bf16(X, M, K, K, T2b, ldm8, s);
+      if (e == cudaSuccess) e = launch_transpose_bf16(hp, M, Ho, Ho, T4b, ldm8, s);
+      nl += 2;
+    } else if (tw) {
       e = launch_transpose_bf16(DA, M, G, G, T1b, ldm8, s);
       if (e == cudaSuccess) e = launch_transpose_bf16(X, M, K, K, T2b, ldm8, s);
       if (e == cudaSuccess && cell == RCU_GRU) e = launch_transpose_bf16(DR, M, G, G, T3b, ldm8, s);
@@ -1426,20 +1445,25 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     nl += 2;
     h->end(s);
     h->begin("bwd_colsum", s);
-    if (e == cudaSuccess) e = launch_colsum(DA, M, G, csum, gbih, s);
-    if (e == cudaSuccess) e = launch_colsum(DR, M, G, csum, gbhh, s);
+    // (with the kernel's per-batch-group sums, over nbg rows instead of M)
+    if (e == cudaSuccess) e = launch_colsum(tcd ? BS : DA, tcd ? nbg : M, G, csum, gbih, s);
+    if (e == cudaSuccess)
+      e = launch_colsum(tcd ? BS + (size_t)nbg * G : DR, tcd ? nbg : M, G, csum, gbhh, s);
     nl += 4;
     h->end(s);
     h->begin("bwd_dx_gemm", s);
     if (e == cudaSuccess && dX) {
       if (tw) {
-        __nv_bfloat16 *DAb = bws + b_da, *WTb = bws + b_wt;
-        e = launch_convert_rows_bf16(DA, M, G, G, DAb, g8, s);
+        __nv_bfloat16 *WTb = bws + b_wt;
+        if (!tcd) {
+          e = launch_convert_rows_bf16(DA, M, G, G, DAb, g8, s);
+          nl += 1;
+        }
         if (e == cudaSuccess) e = launch_transpose_bf16(Wih, G, K, ldk, WTb, g8, s);
         if (e == cudaSuccess)
           e = launch_tc_gemm(DAb, g8, WTb, g8, nullptr, dX, K, M, nullptr, K, G, h->nsm, s, err,
                              (uint64_t)h->timeout_ns);
-        nl += 3;
+        nl += 2;
       } else {
         e = launch_gemm_simt<float, float>(DA, G, WT, G, nullptr, dX, K, M, nullptr, K, G, s, err);
         nl += 1;

@@ -61,6 +61,8 @@ struct BCtl {
   // peer_sent[r] = steps whose partial sums cluster rank r sent to this CTA,
   // stored here by rank r itself before the final cluster barrier
   uint32_t peer_sent[4];
+  // per lane quarter: the column sums of DA and DR over its 32 rows
+  float bred[4][2][3][UNITS];
 };
 
 struct BGeo {
@@ -77,7 +79,7 @@ __host__ __device__ inline BGeo make_bgeo(int G, int KS) {
   g.w_bytes = (size_t)g.nkbm * g.N * 128;
   // partial sums received from the other KS-1 CTAs: [KS-1][4 parts][128 rows] float4
   g.x_bytes = (size_t)(KS - 1) * 4 * BG * 16;
-  const size_t fixed = 1024 + g.w_bytes + g.x_bytes + 256;
+  const size_t fixed = 1024 + g.w_bytes + g.x_bytes + 2048;  // + the control block
   const int st = (int)((SMEM_LIMIT - (long long)fixed) / A_STAGE);
   g.stages = st > MAX_STAGES ? MAX_STAGES : st;
   g.smem = fixed + (size_t)(g.stages > 0 ? g.stages : 0) * A_STAGE;
@@ -295,6 +297,11 @@ __device__ __forceinline__ void bwd_body(const BMaps &maps, const TcBwdParams &p
     }
     int x_posted = 0, x_done = 0;  // thread 64: phases armed / completed
     float dhz[UPT], act[6][UPT];   // carried z dh; the step's saved activations
+    float sa[3][UPT], sr[3][UPT];  // this row's sums of DA and DR over the steps
+#pragma unroll
+    for (int g = 0; g < 3; ++g)
+#pragma unroll
+      for (int j = 0; j < UPT; ++j) sa[g][j] = sr[g][j] = 0.f;
 #pragma unroll
     for (int j = 0; j < UPT; ++j) dhz[j] = (row_ok && p.dhn) ? p.dhn[(size_t)b * H + ub + j] : 0.f;
     // the activations of step t for this row and units: r, z, n, hn, h', dy
@@ -380,6 +387,13 @@ __device__ __forceinline__ void bwd_body(const BMaps &maps, const TcBwdParams &p
           dr[0][j] = ar; dr[1][j] = az; dr[2][j] = an * rg;
           dhz[j] = dh * z;
         }
+#pragma unroll
+        for (int g = 0; g < 3; ++g)
+#pragma unroll
+          for (int j = 0; j < UPT; ++j) {
+            sa[g][j] += da[g][j];
+            sr[g][j] += dr[g][j];
+          }
         // the next step's MMA operand first: it is on the critical path
         __nv_bfloat16 *xo = p.xdr + ((size_t)(t & 1) * B + b) * p.Kx + ub;
 #pragma unroll
@@ -397,16 +411,71 @@ __device__ __forceinline__ void bwd_body(const BMaps &maps, const TcBwdParams &p
       if (threadIdx.x == 64)
         red_release_gpu_add(ctr, (p.drop_arrival && blockIdx.x == 0 && s == 0) ? 0u : 1u);
       if (row_ok) {
-        // off the critical path: the gate gradients for the weight GEMMs
+        // off the critical path: the gate gradients for the GEMMs after the loop
+        if (p.DA) {
 #pragma unroll
-        for (int g = 0; g < 3; ++g) {
-          st4(p.DA + row * G + (size_t)g * H + ub, da[g][0], da[g][1], da[g][2], da[g][3]);
-          st4(p.DR + row * G + (size_t)g * H + ub, dr[g][0], dr[g][1], dr[g][2], dr[g][3]);
+          for (int g = 0; g < 3; ++g) {
+            st4(p.DA + row * G + (size_t)g * H + ub, da[g][0], da[g][1], da[g][2], da[g][3]);
+            st4(p.DR + row * G + (size_t)g * H + ub, dr[g][0], dr[g][1], dr[g][2], dr[g][3]);
+          }
+        }
+        if (p.dat) {
+          // transposed: a warp's 32 rows are 32 consecutive elements
+#pragma unroll
+          for (int g = 0; g < 3; ++g)
+#pragma unroll
+            for (int j = 0; j < UPT; ++j) {
+              const size_t c = (size_t)(g * H + ub + j) * p.ldt + row;
+              p.dat[c] = __float2bfloat16_rn(da[g][j]);
+              p.drt[c] = __float2bfloat16_rn(dr[g][j]);
+            }
+        }
+        if (p.dab) {
+#pragma unroll
+          for (int g = 0; g < 3; ++g) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(da[g][0], da[g][1]);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(da[g][2], da[g][3]);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t *>(&lo);
+            pk.y = *reinterpret_cast<uint32_t *>(&hi);
+            *reinterpret_cast<uint2 *>(p.dab + row * p.ldab + (size_t)g * H + ub) = pk;
+          }
         }
       }
       load_act(t - 1);
     }
     if (threadIdx.x == 64) x_left = x_done < x_posted ? -x_done - 1 : x_done;
+    if (p.bsum) {
+      // the batch group's column sums of DA and DR over this CTA's units:
+      // across the warp's 32 rows by shuffles, then across the 4 lane
+      // quarters in a fixed order (deterministic)
+#pragma unroll
+      for (int g = 0; g < 3; ++g)
+#pragma unroll
+        for (int j = 0; j < UPT; ++j)
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) {
+            sa[g][j] += __shfl_xor_sync(0xffffffffu, sa[g][j], off);
+            sr[g][j] += __shfl_xor_sync(0xffffffffu, sr[g][j], off);
+          }
+      if (lane == 0) {
+#pragma unroll
+        for (int g = 0; g < 3; ++g)
+#pragma unroll
+          for (int j = 0; j < UPT; ++j) {
+            ctl->bred[q][0][g][part * UPT + j] = sa[g][j];
+            ctl->bred[q][1][g][part * UPT + j] = sr[g][j];
+          }
+      }
+      epi_bar();
+      const int e = threadIdx.x - 64;  // 2 x 3 x 16 sums
+      if (e < 2 * 3 * UNITS) {
+        const int w = e / (3 * UNITS), g = (e / UNITS) % 3, u = e % UNITS;
+        const float v = ctl->bred[0][w][g][u] + ctl->bred[1][w][g][u] + ctl->bred[2][w][g][u] +
+                        ctl->bred[3][w][g][u];
+        p.bsum[((size_t)w * ceil_div(B, BG) + bg) * G + (size_t)g * H + u0 + u] = v;
+      }
+    }
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -471,8 +540,10 @@ cudaError_t launch_tc_bwd(const TcBwdParams &pin, int nsm, cudaStream_t s) {
   if (ks == 0) return cudaErrorInvalidValue;
   auto aligned16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
   if ((p.Kx % 8) || p.Kx < G || !aligned16(p.gates) || !aligned16(p.zh) || !aligned16(p.hp) ||
-      !aligned16(p.dy) || !aligned16(p.DA) || !aligned16(p.DR) || (p.dh0 && !aligned16(p.dh0)) ||
-      !aligned16(p.xdr) || !aligned16(p.wt))
+      !aligned16(p.dy) || (p.DA && (!aligned16(p.DA) || !p.DR || !aligned16(p.DR))) ||
+      (p.dh0 && !aligned16(p.dh0)) || !aligned16(p.xdr) || !aligned16(p.wt) ||
+      (p.dat && (!p.drt || p.ldt < p.T * p.B)) || (p.dab && (!aligned16(p.dab) || (p.ldab % 8) ||
+                                                             p.ldab < G)))
     return cudaErrorInvalidValue;
   BMaps maps;
   maps.a_rows = NBG == 1 ? round_up(p.B, 8) : BG;

@@ -62,7 +62,17 @@ struct TcBwdParams {
   const float *hp;     // [T*B][H]: h_{t-1}
   const float *dy;     // [T*B][H]
   const float *dhn;    // [B][H] or NULL
-  float *DA, *DR;      // [T*B][3H]
+  float *DA, *DR;      // [T*B][3H] fp32, or NULL
+  // the same gradients as the tensor-core GEMMs after the loop read them, or
+  // NULL: DA^T and DR^T in bf16 ([3H][ldt], ldt a multiple of 8 >= T*B; the
+  // weight-gradient operands), DA in bf16 ([T*B][ldab]; the input-gradient
+  // operand), and the column sums of DA and DR over each batch group's rows
+  // ([2][ceil(B/128)][3H] fp32, in a fixed order: the bias gradients)
+  __nv_bfloat16 *dat, *drt;
+  int ldt;
+  __nv_bfloat16 *dab;
+  int ldab;
+  float *bsum;
   float *dh0;          // [B][H] or NULL
   __nv_bfloat16 *xdr;  // [2][B][Kx]: dR_t exchange, bf16 (buffer t & 1)
   int Kx;              // its row stride (a multiple of 8, >= 3H)
