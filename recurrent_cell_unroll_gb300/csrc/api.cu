@@ -1302,10 +1302,15 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     }
     h->end(s);
     const float *c0l = c0 ? c0 + (size_t)i * B * H : nullptr;
-    h->begin("bwd_prep", s);
-    if (e == cudaSuccess)
-      e = launch_bwd_prep(T, B, H, cell, zin, zh, c0l, cs, ms, s, CR, h->cclip_lo, h->cclip_hi);
-    h->end(s);
+    // the tcgen05 GRU reverse-time kernel (below) activates the gates itself
+    const bool tcb = tcg && cell == RCU_GRU && P == 0 && !lengths && tc_bwd_supported(H, B, h->nsm);
+    if (!tcb) {
+      h->begin("bwd_prep", s);
+      if (e == cudaSuccess)
+        e = launch_bwd_prep(T, B, H, cell, zin, zh, c0l, cs, ms, s, CR, h->cclip_lo, h->cclip_hi);
+      h->end(s);
+      nl += 1;
+    }
     if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: recompute: %s", cudaGetErrorString(e));
     // projection: dy' = dy (+ dh_n at the last step), A = dy' W_hr, F = W_hh W_hr
     const float *rec_dy = dYdir, *rec_W = (const float *)lw.whh_plain.p;
@@ -1337,7 +1342,6 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     // the weight and input gradients on the tensor cores (below)
     const bool tw = tcg && (K % 4) == 0 && (Ho % 4) == 0 && (G % 4) == 0 && aligned16(gWih) &&
                     aligned16(gWhh) && (!dX || aligned16(dX));
-    const bool tcb = tcg && cell == RCU_GRU && P == 0 && !lengths && tc_bwd_supported(H, B, h->nsm);
     // with both, the reverse-time kernel writes the gate gradients straight
     // in the forms those GEMMs read (DA^T, DR^T and DA in bf16, the bias sums
     // per batch group): no fp32 DA / DR, transposes or column sums of them
@@ -1351,7 +1355,7 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
       e = launch_transpose_bf16((const float *)lw.whh_plain.p, G, H, ldo, WTh, g8, s);
       TcBwdParams q{};
       q.T = T; q.B = B; q.H = H;
-      q.gates = zin; q.zh = zh; q.hp = hp; q.dy = rec_dy;
+      q.zin = zin; q.zh = zh; q.hp = hp; q.dy = rec_dy;
       q.dhn = dhnl;
       if (tcd) {
         q.dat = T1b; q.drt = T3b; q.ldt = ldm8;
@@ -1471,8 +1475,8 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     }
     h->end(s);
     if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: gradients: %s", cudaGetErrorString(e));
-    // plus prep; projection: 3 GEMMs, 4 transposes, up to 2 adds
-    launches += nl + 1 + (P > 0 ? 7 + (dhnl ? 1 : 0) + (T > 1 ? 1 : 0) : 0);
+    // projection: 3 GEMMs, 4 transposes, up to 2 adds
+    launches += nl + (P > 0 ? 7 + (dhnl ? 1 : 0) + (T > 1 ? 1 : 0) : 0);
     return RCU_OK;
   };
 

@@ -18,13 +18,15 @@
 // peer the partial sums of the peer's 16 units through distributed shared
 // memory (st.async, counted on the peer's mbarrier), and finalises 16 units.
 // Its 16 epilogue warps (thread = batch row = TMEM lane, 4 units) then form
-// dh_t and the gate gradients of step t from the saved activations,
+// dh_t and the gate gradients of step t,
 //     dn = dh (1 - z), dz = dh (h' - n), an = dn (1 - n^2),
 //     ar = an hn r (1 - r), az = dz z (1 - z)       (hn = W_hn h' + b_hn),
 //     DA = [ar, az, an], DR = [ar, az, an r],        carried z dh,
-// write both (fp32) for the weight-gradient GEMMs, and publish DR_t in bf16
-// (the precision of every MMA operand of the bf16 forward) with one
-// red.release per CTA on a bounded step counter per batch group.
+// with the gates r, z, n activated a step ahead from the recomputed
+// pre-activations of both sides, write the gradients for the GEMMs after
+// the loop, and publish DR_t in bf16 (the precision of every MMA operand of
+// the bf16 forward) with one red.release per CTA on a bounded step counter
+// per batch group.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -305,20 +307,35 @@ __device__ __forceinline__ void bwd_body(const BMaps &maps, const TcBwdParams &p
 #pragma unroll
     for (int j = 0; j < UPT; ++j) dhz[j] = (row_ok && p.dhn) ? p.dhn[(size_t)b * H + ub + j] : 0.f;
     // the activations of step t for this row and units: r, z, n, hn, h', dy
+    // (a step ahead, off the critical path; the gates are activated here
+    // from both sides' pre-activations with the precise fp32 functions)
     auto load_act = [&](int t) {
       if (!row_ok || t < 0) return;
       const size_t row = (size_t)t * B + b;
-      const float *g = p.gates + row * G + ub;
-      float4 v[6];
-      v[0] = ldg4(g);
-      v[1] = ldg4(g + H);
-      v[2] = ldg4(g + 2 * H);
-      v[3] = ldg4(p.zh + row * G + 2 * H + ub);
-      v[4] = ldg4(p.hp + row * H + ub);
-      v[5] = ldg4(p.dy + row * H + ub);
+      const float *a = p.zin + row * G + ub, *hz = p.zh + row * G + ub;
+      float4 v[8];
+      v[0] = ldg4(a);
+      v[1] = ldg4(a + H);
+      v[2] = ldg4(a + 2 * H);
+      v[3] = ldg4(hz);
+      v[4] = ldg4(hz + H);
+      v[5] = ldg4(hz + 2 * H);
+      v[6] = ldg4(p.hp + row * H + ub);
+      v[7] = ldg4(p.dy + row * H + ub);
+      float f[8][UPT];
 #pragma unroll
-      for (int k = 0; k < 6; ++k) {
-        act[k][0] = v[k].x; act[k][1] = v[k].y; act[k][2] = v[k].z; act[k][3] = v[k].w;
+      for (int k = 0; k < 8; ++k) {
+        f[k][0] = v[k].x; f[k][1] = v[k].y; f[k][2] = v[k].z; f[k][3] = v[k].w;
+      }
+#pragma unroll
+      for (int j = 0; j < UPT; ++j) {
+        const float rg = sigmoid_f(f[0][j] + f[3][j]);
+        act[0][j] = rg;
+        act[1][j] = sigmoid_f(f[1][j] + f[4][j]);
+        act[2][j] = tanh_f(f[2][j] + rg * f[5][j]);
+        act[3][j] = f[5][j];
+        act[4][j] = f[6][j];
+        act[5][j] = f[7][j];
       }
     };
     load_act(T - 1);
@@ -539,7 +556,7 @@ cudaError_t launch_tc_bwd(const TcBwdParams &pin, int nsm, cudaStream_t s) {
   int ks = choose_ks(H);
   if (ks == 0) return cudaErrorInvalidValue;
   auto aligned16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
-  if ((p.Kx % 8) || p.Kx < G || !aligned16(p.gates) || !aligned16(p.zh) || !aligned16(p.hp) ||
+  if ((p.Kx % 8) || p.Kx < G || !aligned16(p.zin) || !aligned16(p.zh) || !aligned16(p.hp) ||
       !aligned16(p.dy) || (p.DA && (!aligned16(p.DA) || !p.DR || !aligned16(p.DR))) ||
       (p.dh0 && !aligned16(p.dh0)) || !aligned16(p.xdr) || !aligned16(p.wt) ||
       (p.dat && (!p.drt || p.ldt < p.T * p.B)) || (p.dab && (!aligned16(p.dab) || (p.ldab % 8) ||

@@ -57,8 +57,8 @@ bool tc_launch_clustered(const void *fn, int grid, int nthreads, int cs, size_t 
 // MMA operand, and finally dh0 = z_0 dh_0 + W_hh^T dR_0.
 struct TcBwdParams {
   int T, B, H;
-  const float *gates;  // [T*B][3H]: activated r, z, n
-  const float *zh;     // [T*B][3H]: hidden-side pre-activations (n part: W_hn h' + b_hn)
+  const float *zin;    // [T*B][3H]: input-side pre-activations X W_ih^T + b_ih
+  const float *zh;     // [T*B][3H]: hidden-side pre-activations H_prev W_hh^T + b_hh
   const float *hp;     // [T*B][H]: h_{t-1}
   const float *dy;     // [T*B][H]
   const float *dhn;    // [B][H] or NULL
