@@ -34,7 +34,6 @@ namespace {
 constexpr int UNITS = 16;       // hidden units each CTA finalises
 constexpr int BG = 128;         // batch rows per CTA (MMA M)
 constexpr int BK = 64;          // K per stage (128 bytes of bf16)
-constexpr int A_STAGE = BG * BK * 2;
 constexpr int EPI_WARPS = 16;   // 4 per TMEM lane quarter
 constexpr int UPT = UNITS / 4;  // units per epilogue thread
 constexpr int NT = 64 + 32 * EPI_WARPS;  // warp 0 TMA, warp 1 MMA, then the epilogue
@@ -85,10 +84,14 @@ struct Geo {
   size_t w_bytes, x_bytes, g_bytes, o_bytes, smem;
 };
 
-// tiles (the Maps::tiles mask): reserve the G tile [nG][128 rows][16 units]
-// fp32 and the output tiles [128 rows][16 units] of the tiled streams (fp32
-// y: 8 KB, bf16 rows: 4 KB)
-__host__ __device__ inline Geo make_geo(int nG, int K, int KS, int tiles = 0) {
+// tiles (the Maps::tiles mask): reserve the G tile [nG][ar rows][16 units]
+// fp32 and the output tiles [ar rows][16 units] of the tiled streams (fp32 y,
+// bf16 rows).  ar = the h rows a stage holds (Maps::a_rows): 128, or fewer
+// when one batch group holds the whole batch, so that a small batch keeps
+// more K blocks in flight.  The MMA still reads 128 rows from each stage
+// (M = 128); rows past ar fall on the next stage or on the slack reserved
+// after the ring, and only feed accumulator rows the epilogue never uses.
+__host__ __device__ inline Geo make_geo(int nG, int K, int KS, int tiles = 0, int ar = BG) {
   Geo g;
   g.N = nG * UNITS * KS;
   g.nkb = ceil_div(K, BK);
@@ -96,12 +99,13 @@ __host__ __device__ inline Geo make_geo(int nG, int K, int KS, int tiles = 0) {
   g.w_bytes = (size_t)g.nkbm * g.N * 128;
   // partial sums received from the other KS-1 CTAs: [KS-1][nG][4][128] float4
   g.x_bytes = (size_t)(KS - 1) * nG * 4 * BG * 16;
-  g.g_bytes = tiles ? (size_t)nG * BG * UNITS * 4 : 0;
-  g.o_bytes = (size_t)((tiles & 1) ? BG * UNITS * 4 : 0) + ((tiles & 2) ? BG * UNITS * 2 : 0);
-  const size_t fixed = 1024 + g.w_bytes + g.x_bytes + g.g_bytes + g.o_bytes + 256;
-  int st = (int)((SMEM_LIMIT - (long long)fixed) / A_STAGE);
+  g.g_bytes = tiles ? (size_t)nG * ar * UNITS * 4 : 0;
+  g.o_bytes = (size_t)((tiles & 1) ? ar * UNITS * 4 : 0) + ((tiles & 2) ? ar * UNITS * 2 : 0);
+  const size_t stage = (size_t)ar * BK * 2, slack = (size_t)(BG - ar) * BK * 2;
+  const size_t fixed = 1024 + g.w_bytes + g.x_bytes + g.g_bytes + g.o_bytes + 256 + slack;
+  int st = (int)((SMEM_LIMIT - (long long)fixed) / (long long)stage);
   g.stages = st > MAX_STAGES ? MAX_STAGES : st;
-  g.smem = fixed + (size_t)(g.stages > 0 ? g.stages : 0) * A_STAGE;
+  g.smem = fixed + (size_t)(g.stages > 0 ? g.stages : 0) * stage;
   return g;
 }
 
@@ -167,7 +171,9 @@ __device__ __forceinline__ float tanh_fast(float x) {
 }
 __device__ __forceinline__ float sigmoid_fast(float x) { return fmaf(0.5f, tanh_fast(0.5f * x), 0.5f); }
 
-template <int NG, int KS>
+// FULL: every stage and tile strip holds 128 rows (a_rows == 128, known at
+// compile time); otherwise maps.a_rows rows (one batch group of fewer rows)
+template <int NG, int KS, bool FULL>
 __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p) {
   static_assert(KS == 1 || KS == 2 || KS == 4, "K is split over 1, 2 or 4 CTAs");
   if (KS > 1 && tc::cluster_nctarank() != (uint32_t)KS) {
@@ -180,14 +186,16 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
-  const Geo geo = make_geo(NG, p.Hout, KS, maps.tiles);
+  const int AR = FULL ? BG : maps.a_rows;    // h rows per stage, rows per tile strip
+  const size_t ASTG = (size_t)AR * BK * 2;  // bytes per h stage
+  const Geo geo = make_geo(NG, p.Hout, KS, maps.tiles, AR);
   const int N = geo.N, STG = geo.stages;
   uint8_t *sW = smem;                       // resident B operand, nkbm blocks of N x 128 B
   uint8_t *sA = smem + geo.w_bytes;         // ring of STG stages of 128 x 128 B
-  float4 *xbuf = reinterpret_cast<float4 *>(sA + (size_t)STG * A_STAGE);
+  float4 *xbuf = reinterpret_cast<float4 *>(sA + (size_t)STG * ASTG);
   float *gtile = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(xbuf) + geo.x_bytes);
   uint8_t *otile = reinterpret_cast<uint8_t *>(gtile) + geo.g_bytes;  // fp32 y strips, then
-  uint8_t *otile_m = otile + ((maps.tiles & 1) ? BG * UNITS * 4 : 0);   // the bf16 strips
+  uint8_t *otile_m = otile + ((maps.tiles & 1) ? AR * UNITS * 4 : 0);   // the bf16 strips
   Ctl *ctl = reinterpret_cast<Ctl *>(otile + geo.o_bytes);
 
   const int NU = p.NU, NBG = ceil_div(p.B, BG);  // NU = CTAs per (direction, batch group)
@@ -282,7 +290,7 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
           const int kb = kb0 + i;
           if (!tc::mbar_wait(&ctl->empty[stage], phase ^ 1, p.err, abort, tmo)) goto producer_out;
           tc::mbar_arrive_expect_tx(&ctl->full[stage], (uint32_t)(maps.a_rows * BK * 2));
-          tc::tma_load_2d(sA + (size_t)stage * A_STAGE, &maps.hx, &ctl->full[stage], kb * BK,
+          tc::tma_load_2d(sA + (size_t)stage * ASTG, &maps.hx, &ctl->full[stage], kb * BK,
                           arow);
           pend_stage[npend % MAX_STAGES] = stage;
           pend_phase[npend % MAX_STAGES] = phase;
@@ -336,7 +344,7 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
               stamp(p, step, 10, cyc_issue);
             }
           }
-          const uint64_t ad = adesc0 + (uint64_t)(stage * (A_STAGE >> 4));
+          const uint64_t ad = adesc0 + (uint64_t)((size_t)stage * (ASTG >> 4));
           tc::mma4_bf16_commit(tbase, ad, bd, idesc, i != 0, &ctl->empty[stage]);
           if (tr) cyc_issue += clock64() - c1;
           if (++stage == STG) { stage = 0; phase ^= 1; }
@@ -447,7 +455,7 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
       for (int g = 0; g < NG; ++g)
 #pragma unroll
         for (int q4 = 0; q4 < UNITS / UPT; ++q4)  // strip [g][q4]: 4 units x rows
-          tma_load_3d(gtile + ((size_t)g * (UNITS / UPT) + q4) * BG * UPT, &maps.g, &ctl->gbar,
+          tma_load_3d(gtile + ((size_t)g * (UNITS / UPT) + q4) * AR * UPT, &maps.g, &ctl->gbar,
                       d * NG * H + g * H + u0 + q4 * UPT, row0, tg);
       ++ctl->g_issued;
     };
@@ -473,11 +481,11 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
       }
       epi_bar();
       if (!ctl->go) break;
-      if (tiles) {
+      if (tiles) {  // (rows past AR read past the strip, in bounds; never used)
 #pragma unroll
         for (int g = 0; g < NG; ++g) {
           const float4 f =
-              *reinterpret_cast<const float4 *>(gtile + (((size_t)g * (UNITS / UPT) + part) * BG + r) * UPT);
+              *reinterpret_cast<const float4 *>(gtile + (((size_t)g * (UNITS / UPT) + part) * AR + r) * UPT);
           gx[g][0] = f.x; gx[g][1] = f.y; gx[g][2] = f.z; gx[g][3] = f.w;
         }
       }
@@ -583,10 +591,10 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
           pk.x = *reinterpret_cast<uint32_t *>(&lo);
           pk.y = *reinterpret_cast<uint32_t *>(&hi);
           // bf16 strips of 8 units (16-byte rows): part pairs share one
-          *reinterpret_cast<uint2 *>(otile_m + (((size_t)(part >> 1) * BG + r) * 2 * UPT + (part & 1) * UPT) * 2) = pk;
+          *reinterpret_cast<uint2 *>(otile_m + (((size_t)(part >> 1) * AR + r) * 2 * UPT + (part & 1) * UPT) * 2) = pk;
         }
         if (maps.tiles & 1)
-          *reinterpret_cast<float4 *>(otile + ((size_t)part * BG + r) * UPT * 4) =
+          *reinterpret_cast<float4 *>(otile + ((size_t)part * AR + r) * UPT * 4) =
               make_float4(h[0], h[1], h[2], h[3]);
         fence_proxy_async_shared();
       }
@@ -607,11 +615,11 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
             const int ts = d == 0 ? step : Tg - 1 - step;
             if (maps.tiles & 1)
               for (int q4 = 0; q4 < UNITS / UPT; ++q4)
-                tma_store_3d(&maps.out, otile + (size_t)q4 * BG * UPT * 4,
+                tma_store_3d(&maps.out, otile + (size_t)q4 * AR * UPT * 4,
                              d * p.Hout + u0 + q4 * UPT, row0, ts);
             if (maps.tiles & 2)
               for (int q8 = 0; q8 < UNITS / (2 * UPT); ++q8)
-                tma_store_3d(&maps.outm, otile_m + (size_t)q8 * BG * 2 * UPT * 2,
+                tma_store_3d(&maps.outm, otile_m + (size_t)q8 * AR * 2 * UPT * 2,
                              d * p.Hout + u0 + q8 * 2 * UPT, row0, ts);
           }
           if (step + 1 < Tg) issue_g(step + 1);
@@ -705,23 +713,23 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
 }
 
 // K kept whole
-template <int NG>
+template <int NG, bool FULL>
 __global__ void __launch_bounds__(NT, 1) rec_tc_kernel(const __grid_constant__ Maps maps,
                                                        const RecParams p) {
-  rec_tc_body<NG, 1>(maps, p);
+  rec_tc_body<NG, 1, FULL>(maps, p);
 }
 // K split over a CTA pair; the pair is the kernel's own cluster shape
-template <int NG>
+template <int NG, bool FULL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT, 1)
     rec_tc_pair_kernel(const __grid_constant__ Maps maps, const RecParams p) {
-  rec_tc_body<NG, 2>(maps, p);
+  rec_tc_body<NG, 2, FULL>(maps, p);
 }
 // K split over 4 CTAs (GRU: the resident weights and the partial-sum buffer
 // fit beside a 3-stage h ring)
-template <int NG>
+template <int NG, bool FULL>
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(NT, 1)
     rec_tc_quad_kernel(const __grid_constant__ Maps maps, const RecParams p) {
-  rec_tc_body<NG, 4>(maps, p);
+  rec_tc_body<NG, 4, FULL>(maps, p);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -822,10 +830,11 @@ void tc_pack_whh(int cell, int H, int Hout, const float *whh, std::vector<uint16
 
 namespace {
 
-template <int NG>
+template <int NG, bool FULL>
 const void *kernel_for(int ks) {
-  if (ks == 4) return (const void *)rec_tc_quad_kernel<NG>;
-  return ks == 2 ? (const void *)rec_tc_pair_kernel<NG> : (const void *)rec_tc_kernel<NG>;
+  if (ks == 4) return (const void *)rec_tc_quad_kernel<NG, FULL>;
+  return ks == 2 ? (const void *)rec_tc_pair_kernel<NG, FULL>
+                 : (const void *)rec_tc_kernel<NG, FULL>;
 }
 // a K split over ks CTAs fits: a ring of at least 2 h stages and a K block
 // for every CTA
@@ -899,8 +908,8 @@ cudaError_t launch_tc_recurrent(const TcRecParams &tp, int nsm, cudaStream_t s) 
   const int tmask = (y_out ? 1 : 0) | (m_out ? 2 : 0);
 
   for (int attempt = 0; attempt < 3; ++attempt) {
-    maps.tiles = tiles_ok && make_geo(nG, p.Hout, ks, tmask).stages >= 4 ? tmask : 0;
-    const Geo geo = make_geo(nG, p.Hout, ks, maps.tiles);
+    maps.tiles = tiles_ok && make_geo(nG, p.Hout, ks, tmask, maps.a_rows).stages >= 4 ? tmask : 0;
+    const Geo geo = make_geo(nG, p.Hout, ks, maps.tiles, maps.a_rows);
     if (maps.tiles &&
         (!make_map_steps(&maps.g, p.G, false, p.T, p.B, p.ldG, p.ldG, maps.a_rows) ||
          (y_out && !make_map_steps(&maps.out, p.y, false, p.T, p.B, ldo, ldo, maps.a_rows)) ||
@@ -912,7 +921,9 @@ cudaError_t launch_tc_recurrent(const TcRecParams &tp, int nsm, cudaStream_t s) 
       if (!make_map(&maps.w[d], w, (long long)NU16 * nG * UNITS, p.Hout, p.Kp, geo.N))
         return cudaErrorInvalidValue;
     }
-    const void *fn = nG == 4 ? kernel_for<4>(ks) : kernel_for<3>(ks);
+    const bool full = maps.a_rows == BG;
+    const void *fn = nG == 4 ? (full ? kernel_for<4, true>(ks) : kernel_for<4, false>(ks))
+                             : (full ? kernel_for<3, true>(ks) : kernel_for<3, false>(ks));
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)geo.smem);
     if (e != cudaSuccess) return e;
