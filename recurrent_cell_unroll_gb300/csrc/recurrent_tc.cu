@@ -98,7 +98,7 @@ __host__ __device__ inline Geo make_geo(int nG, int K, int KS, int tiles = 0, in
   g.nkbm = ceil_div(g.nkb, KS);
   g.w_bytes = (size_t)g.nkbm * g.N * 128;
   // partial sums received from the other KS-1 CTAs: [KS-1][nG][4][128] float4
-  g.x_bytes = (size_t)(KS - 1) * nG * 4 * BG * 16;
+  g.x_bytes = (size_t)(KS - 1) * nG * 4 * ar * 16;  // (the live rows only)
   g.g_bytes = tiles ? (size_t)nG * ar * UNITS * 4 : 0;
   g.o_bytes = (size_t)((tiles & 1) ? ar * UNITS * 4 : 0) + ((tiles & 2) ? ar * UNITS * 2 : 0);
   const size_t stage = (size_t)ar * BK * 2, slack = (size_t)(BG - ar) * BK * 2;
@@ -382,7 +382,7 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
     // among pr's peers): slot*(NG*4*128) + (g*4 + part)*128 + r, one float4 per
     // (gate, thread).
     constexpr int NP = KS > 1 ? KS - 1 : 1;
-    constexpr int SLOT = NG * 4 * BG;  // float4 per slot
+    const int SLOT = NG * 4 * AR;  // float4 per slot (rows past AR are never sent)
     uint32_t peer_x[NP], peer_bar[NP], peer_col[NP];
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
@@ -511,20 +511,23 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
         for (int g = 0; g < NG; ++g)
 #pragma unroll
           for (int j = 0; j < UPT; ++j) acc[g][j] = __uint_as_float(ra[g][j]);
-        if (KS > 1) {
+        if (KS > 1 && (FULL || r < AR)) {
           // hand each peer its units' partial sums over K blocks [kb0, kb0+nk)
+          // (the batch's rows only: the distributed-shared-memory bandwidth
+          // is the cost of this exchange)
 #pragma unroll
           for (int i = 0; i < NP; ++i)
 #pragma unroll
             for (int g = 0; g < NG; ++g) {
               const int gi = KS > 1 ? g : 0;
-              tc::st_async_v4(peer_x[i] + (uint32_t)(((g * 4 + part) * BG + r) * 16),
+              tc::st_async_v4(peer_x[i] + (uint32_t)(((g * 4 + part) * AR + r) * 16),
                               __uint_as_float(rp[i][gi][0]), __uint_as_float(rp[i][gi][1]),
                               __uint_as_float(rp[i][gi][2]), __uint_as_float(rp[i][gi][3]),
                               peer_bar[i]);
             }
-          if (threadIdx.x == 64) x_sent = (uint32_t)(step + 1);
         }
+        // (thread 64 counts the steps sent, whether or not its own row is live)
+        if (KS > 1 && threadIdx.x == 64) x_sent = (uint32_t)(step + 1);
       }
       if (p.trace && threadIdx.x == 64) stamp(p, step, 5, globaltimer_ns());
       if (KS > 1) {
@@ -537,13 +540,15 @@ __device__ __forceinline__ void rec_tc_body(const Maps &maps, const RecParams &p
         }
         epi_bar();
         if (!ctl->go2) break;
+        if (FULL || r < AR) {
 #pragma unroll
-        for (int i = 0; i < NP; ++i)
+          for (int i = 0; i < NP; ++i)
 #pragma unroll
-          for (int g = 0; g < NG; ++g) {
-            const float4 v = xbuf[(size_t)i * SLOT + (g * 4 + part) * BG + r];
-            acc[g][0] += v.x; acc[g][1] += v.y; acc[g][2] += v.z; acc[g][3] += v.w;
-          }
+            for (int g = 0; g < NG; ++g) {
+              const float4 v = xbuf[(size_t)i * SLOT + (g * 4 + part) * AR + r];
+              acc[g][0] += v.x; acc[g][1] += v.y; acc[g][2] += v.z; acc[g][3] += v.w;
+            }
+        }
         if (p.trace && threadIdx.x == 64) stamp(p, step, 11, globaltimer_ns());
       }
       if (active) {
