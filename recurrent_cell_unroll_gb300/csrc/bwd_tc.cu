@@ -312,6 +312,7 @@ __device__ __forceinline__ void bwd_body(const BMaps &maps, const TcBwdParams &p
     auto load_act = [&](int t) {
       if (!row_ok || t < 0) return;
       const size_t row = (size_t)t * B + b;
+      if (!RCU_DCHECK(row < (size_t)T * B && ub + UPT <= H, p.err)) return;
       const float *a = p.zin + row * G + ub, *hz = p.zh + row * G + ub;
       float4 v[8];
       v[0] = ldg4(a);
@@ -380,7 +381,7 @@ __device__ __forceinline__ void bwd_body(const BMaps &maps, const TcBwdParams &p
       }
       if (t < 0) {
         // dh_{-1}: the gradient reaching h0
-        if (row_ok && p.dh0)
+        if (row_ok && p.dh0 && RCU_DCHECK(ub + UPT <= H, p.err))
           st4(p.dh0 + (size_t)b * H + ub, dhz[0] + acc[0], dhz[1] + acc[1], dhz[2] + acc[2],
               dhz[3] + acc[3]);
         break;
@@ -389,7 +390,7 @@ __device__ __forceinline__ void bwd_body(const BMaps &maps, const TcBwdParams &p
       // ragged batch tail hold rows on both sides of B)
       const size_t row = (size_t)t * B + b;
       float da[3][UPT], dr[3][UPT];
-      if (row_ok) {
+      if (row_ok && RCU_DCHECK(t < T && (size_t)(2 * H + ub + UPT) <= (size_t)p.Kx, p.err)) {
 #pragma unroll
         for (int j = 0; j < UPT; ++j) {
           const float rg = act[0][j], z = act[1][j], n = act[2][j], hn = act[3][j],
@@ -427,7 +428,7 @@ __device__ __forceinline__ void bwd_body(const BMaps &maps, const TcBwdParams &p
       epi_bar();
       if (threadIdx.x == 64)
         red_release_gpu_add(ctr, (p.drop_arrival && blockIdx.x == 0 && s == 0) ? 0u : 1u);
-      if (row_ok) {
+      if (row_ok && RCU_DCHECK(row < (size_t)T * B && (!p.dat || row < (size_t)p.ldt), p.err)) {
         // off the critical path: the gate gradients for the GEMMs after the loop
         if (p.DA) {
 #pragma unroll
@@ -490,7 +491,8 @@ __device__ __forceinline__ void bwd_body(const BMaps &maps, const TcBwdParams &p
         const int w = e / (3 * UNITS), g = (e / UNITS) % 3, u = e % UNITS;
         const float v = ctl->bred[0][w][g][u] + ctl->bred[1][w][g][u] + ctl->bred[2][w][g][u] +
                         ctl->bred[3][w][g][u];
-        p.bsum[((size_t)w * ceil_div(B, BG) + bg) * G + (size_t)g * H + u0 + u] = v;
+        if (RCU_DCHECK(bg < ceil_div(B, BG) && u0 + u < H, p.err))
+          p.bsum[((size_t)w * ceil_div(B, BG) + bg) * G + (size_t)g * H + u0 + u] = v;
       }
     }
   }

@@ -44,6 +44,23 @@ for spec, path in cases:
     e = float(np.abs(y.cpu().numpy() - ref[0]).max() / np.abs(ref[0]).max())
     assert e <= (2e-2 if spec.dtype == "bf16" else 1e-4), (spec.name, e)
     net.close()
+# the tcgen05 reverse-time kernel of the GRU (two batch groups, the second ragged)
+spec = wl.GRU_3L.scaled(T=6, B=150, in_dim=24, hidden=64, layers=2, h0_std=0.5)
+inp = wl.make_rnn_inputs(spec, seed=33)
+dy = torch.randn((spec.T, spec.B, spec.hidden), generator=torch.Generator().manual_seed(33))
+net = binding.RNN.from_spec(spec)
+net.set_weights(inp["weights"])
+net.set_attr(binding.RCU_ATTR_PROFILE, 1)
+dx, dh0, _, _ = net.backward(inp["x"].to(dev), dy.to(dev), h0=inp["h0"].to(dev))
+st = net.status()
+assert st == 0, (spec.name, st, binding.load().rcu_last_error())
+assert "bwd_recurrent_tc" in net.profile(), net.profile()
+ref = oracle.rnn_backward(oracle.GRU, inp["x"], inp["weights"], dy, hidden=spec.hidden,
+                          h0=inp["h0"], bf16_weights=True)
+for got, want in ((dx, ref["dx"]), (dh0, ref["dh0"])):
+    e = float(np.abs(got.cpu().numpy() - want).max() / np.abs(want).max())
+    assert e <= 2e-2, ("backward", e)
+net.close()
 print("debug build ok")
 """
 
