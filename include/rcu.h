@@ -76,7 +76,10 @@ typedef struct rcu_rssm_s *rcu_rssm_t;
                                          skips its first state broadcast.  The waits must
                                          time out (RCU_ERR_TIMEOUT from *_get_status). */
 #define RCU_ATTR_FORCE_PATH 3         /* 0 = automatic, 1 = portable SIMT kernels only,
-                                         2 = tensor-core (tcgen05) kernels where supported,
+                                         2 = tensor-core (tcgen05) kernels where supported
+                                         (on an fp32 handle: its GEMMs as fp32-accurate
+                                         three-term bf16 splits at any size; automatic
+                                         mode takes them for large products only),
                                          3 = cluster-resident recurrent kernel where W_hh
                                          fits one thread-block cluster (else SIMT).  On an
                                          RSSM handle: 0 = automatic, 1 = the backward's

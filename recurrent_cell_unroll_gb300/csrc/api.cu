@@ -108,6 +108,7 @@ struct rcu_rnn_s : EventProfiler {
   // the forward's per-layer outputs (layer l < L-1 written to keep_out + l*T*B*Hout)
   DevBuf bw;
   DevBuf bwb;  // bf16 handles: the bf16 operands of the backward's tensor-core GEMMs
+  DevBuf f32x;  // the split bf16 operands of the fp32 GEMMs on the tensor cores
   std::vector<DevBuf> gw;
   bool grads_ready = false;
   float *keep_out = nullptr;
@@ -491,6 +492,28 @@ static int ensure_ws(rcu_rnn_s *h, int T, int B) {
 // from the same bf16(m_{t-1}) and fp32 c_{t-1} as without chunks, so the
 // results equal the unpipelined ones.  The GEMMs that run beside a
 // recurrence use the SMs it leaves free.
+// fp32 C = A B^T + bias (row strides lda, ldb, ldc): on the tensor cores as a
+// three-term bf16 split of both operands (launch_gemm_f32x6: fp32-accurate,
+// small products first, long reductions in chunks) when the product is
+// large enough to pay for the split passes, else the FFMA GEMM.
+// RCU_ATTR_FORCE_PATH = 1 keeps the FFMA GEMM, 2 takes the split one at any
+// size.  *n counts the kernels launched.
+static constexpr double F32X6_MIN_MACS = 2.0e8;
+static cudaError_t gemm_f32(rcu_rnn_t h, const float *A, int lda, const float *B, int ldb,
+                            const float *bias, float *C, int ldc, int M, const int32_t *M_dev,
+                            int N, int K, cudaStream_t s, int *err, int *n) {
+  const bool big = (double)M * N * K >= F32X6_MIN_MACS || h->force_path == 2;
+  if (h->force_path != 1 && big && (!M_dev || K <= 4096) && f32x6_supported(N, ldc, C)) {
+    cudaError_t e = h->f32x.ensure(f32x6_scratch_bytes(M, N, K));
+    if (e != cudaSuccess) return e;
+    *n += f32x6_launches(K);
+    return launch_gemm_f32x6(A, lda, B, ldb, bias, C, ldc, M, M_dev, N, K, h->f32x.p, h->nsm, s,
+                             err, (uint64_t)h->timeout_ns);
+  }
+  *n += 1;
+  return launch_gemm_simt<float, float>(A, lda, B, ldb, bias, C, ldc, M, M_dev, N, K, s, err);
+}
+
 static int lp_chunks(int T) { return std::min(32, std::max(2, T / 64)); }
 
 static bool layer_pipeline_ok(rcu_rnn_t h, int T, int B, bool varlen, bool bf) {
@@ -806,14 +829,15 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
       h->used_tc_gemm = true;
     }
     if (!done) {
+      int nk = 0;
       cudaError_t e = bf ? launch_gemm_simt<__nv_bfloat16, __nv_bfloat16>(
                                (const __nv_bfloat16 *)X, ldx, (const __nv_bfloat16 *)h->wih[l].p,
                                ldw, (const float *)h->gbias[l].p, G, N, Mmax, M_dev, N, K, s, err)
-                         : launch_gemm_simt<float, float>((const float *)X, ldx,
-                                                          (const float *)h->wih[l].p, ldw,
-                                                          (const float *)h->gbias[l].p, G, N,
-                                                          Mmax, M_dev, N, K, s, err);
+                         : gemm_f32(h, (const float *)X, ldx, (const float *)h->wih[l].p, ldw,
+                                    (const float *)h->gbias[l].p, G, N, Mmax, M_dev, N, K, s, err,
+                                    &nk);
       if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "gemm: %s", cudaGetErrorString(e));
+      if (nk > 1) h->launches += nk - 1;  // (the profile range counts one)
     }
     h->end(s);
 
@@ -1292,13 +1316,11 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
                            Ho, h->nsm, s, err, (uint64_t)h->timeout_ns);
       nl += 5;
     } else {
-      e = launch_gemm_simt<float, float>(X, K, Wih, ldk, (const float *)lw.bih_plain.p, zin, G, M,
-                                         nullptr, G, K, s, err);
+      e = gemm_f32(h, X, K, Wih, ldk, (const float *)lw.bih_plain.p, zin, G, M, nullptr, G, K, s,
+                   err, &nl);
       if (e == cudaSuccess)
-        e = launch_gemm_simt<float, float>(hp, Ho, (const float *)lw.whh_plain.p, ldo,
-                                           (const float *)lw.bhh_plain.p, zh, G, M, nullptr, G,
-                                           Ho, s, err);
-      nl += 2;
+        e = gemm_f32(h, hp, Ho, (const float *)lw.whh_plain.p, ldo, (const float *)lw.bhh_plain.p,
+                     zh, G, M, nullptr, G, Ho, s, err, &nl);
     }
     h->end(s);
     const float *c0l = c0 ? c0 + (size_t)i * B * H : nullptr;
@@ -1320,11 +1342,13 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
       CU(cudaMemcpyAsync(dYp, dYdir, TBO * 4, cudaMemcpyDeviceToDevice, s));
       if (dhnl) e = launch_add(dYp + (size_t)(T - 1) * B * Ho, dhnl, (size_t)B * Ho, s);
       if (e == cudaSuccess) e = launch_transpose((const float *)lw.whr_plain.p, P, H, H, WhrT, P, s);
+      int pn = 0;
       if (e == cudaSuccess)
-        e = launch_gemm_simt<float, float>(dYp, Ho, WhrT, P, nullptr, Aw, H, M, nullptr, H, P, s, err);
+        e = gemm_f32(h, dYp, Ho, WhrT, P, nullptr, Aw, H, M, nullptr, H, P, s, err, &pn);
       if (e == cudaSuccess)
-        e = launch_gemm_simt<float, float>((const float *)lw.whh_plain.p, ldo, WhrT, P, nullptr, Fw,
-                                           ldh, G, nullptr, H, P, s, err);
+        e = gemm_f32(h, (const float *)lw.whh_plain.p, ldo, WhrT, P, nullptr, Fw, ldh, G, nullptr,
+                     H, P, s, err, &pn);
+      nl += pn - 2;  // (counted with the projection's fixed launches below)
       h->end(s);
       if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: projection: %s", cudaGetErrorString(e));
       rec_dy = Aw;
@@ -1398,15 +1422,15 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     if (P > 0) {
       h->begin("bwd_proj_grad", s);
       e = launch_transpose((const float *)lw.whh_plain.p, G, Ho, ldo, WhhT, G, s);
-      if (e == cudaSuccess)
-        e = launch_gemm_simt<float, float>(DA, G, WhhT, G, nullptr, Rw, Ho, M, nullptr, Ho, G, s, err);
+      int pn = 0;
+      if (e == cudaSuccess) e = gemm_f32(h, DA, G, WhhT, G, nullptr, Rw, Ho, M, nullptr, Ho, G, s, err, &pn);
       if (e == cudaSuccess && dh0)
         e = cudaMemcpyAsync(dh0 + (size_t)i * B * Ho, Rw, (size_t)B * Ho * 4, cudaMemcpyDeviceToDevice, s);
       if (e == cudaSuccess && T > 1) e = launch_add(dYp, Rw + (size_t)B * Ho, (size_t)(T - 1) * B * Ho, s);
       if (e == cudaSuccess) e = launch_transpose(dYp, M, Ho, Ho, T6, M, s);
       if (e == cudaSuccess) e = launch_transpose(ms, M, H, H, T5, M, s);
-      if (e == cudaSuccess)
-        e = launch_gemm_simt<float, float>(T6, M, T5, M, nullptr, gWhr, H, P, nullptr, H, M, s, err);
+      if (e == cudaSuccess) e = gemm_f32(h, T6, M, T5, M, nullptr, gWhr, H, P, nullptr, H, M, s, err, &pn);
+      nl += pn - 2;
       h->end(s);
       if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: projection gradients: %s", cudaGetErrorString(e));
     }
@@ -1442,9 +1466,10 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
                            err, (uint64_t)h->timeout_ns);
     } else {
       if (e == cudaSuccess)
-        e = launch_gemm_simt<float, float>(T1, M, T2, M, nullptr, gWih, K, G, nullptr, K, M, s, err);
+        e = gemm_f32(h, T1, M, T2, M, nullptr, gWih, K, G, nullptr, K, M, s, err, &nl);
       if (e == cudaSuccess)
-        e = launch_gemm_simt<float, float>(T3, M, T4, M, nullptr, gWhh, Ho, G, nullptr, Ho, M, s, err);
+        e = gemm_f32(h, T3, M, T4, M, nullptr, gWhh, Ho, G, nullptr, Ho, M, s, err, &nl);
+      nl -= 2;
     }
     nl += 2;
     h->end(s);
@@ -1469,8 +1494,7 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
                              (uint64_t)h->timeout_ns);
         nl += 2;
       } else {
-        e = launch_gemm_simt<float, float>(DA, G, WT, G, nullptr, dX, K, M, nullptr, K, G, s, err);
-        nl += 1;
+        e = gemm_f32(h, DA, G, WT, G, nullptr, dX, K, M, nullptr, K, G, s, err, &nl);
       }
     }
     h->end(s);

@@ -216,6 +216,111 @@ bool make_map(CUtensorMap *map, const void *base, int rows, int cols, int ld, in
 
 bool tc_gemm_supported(int K, int N) { return K >= 1 && N >= 1 && N % 4 == 0 && encode_fn(); }
 
+namespace {
+// Three-term bf16 split of an fp32 matrix R x C (row stride ld) into six
+// K segments of kp columns per row (dst row stride 6*kp), in the order that
+// pairs operand A's terms with operand B's: products a1b2, a2b1, a1b3, a2b2,
+// a3b1, then a1b1 (pattern 0 = A: x1 x2 x1 x2 x3 x1; pattern 1 = B: x2 x1
+// x3 x2 x1 x1).  The five small products come first, while the accumulator
+// is still small, so their additions round at their own scale and the sum
+// carries the rounding of the K large additions only, as an FFMA loop does.
+// x1 = bf16(x), x2 = bf16(x - x1), x3 = bf16(x - x1 - x2): both residuals
+// are exact in fp32, so x - (x1 + x2 + x3) is within 2^-24 |x|.  Columns past
+// C are written as zero.
+__global__ void split3_kernel(const float *__restrict__ src, int R, int C, int ld,
+                              __nv_bfloat16 *__restrict__ dst, int kp, int pattern) {
+  for (int r = blockIdx.x; r < R; r += gridDim.x) {
+    __nv_bfloat16 *o = dst + (size_t)r * 6 * kp;
+    for (int c = threadIdx.x; c < kp; c += blockDim.x) {
+      const float x = c < C ? src[(size_t)r * ld + c] : 0.f;
+      const __nv_bfloat16 x1 = __float2bfloat16_rn(x);
+      const float r1 = x - __bfloat162float(x1);
+      const __nv_bfloat16 x2 = __float2bfloat16_rn(r1);
+      const __nv_bfloat16 x3 = __float2bfloat16_rn(r1 - __bfloat162float(x2));
+      if (pattern == 0) {
+        o[c] = x1; o[kp + c] = x2; o[2 * kp + c] = x1;
+        o[3 * kp + c] = x2; o[4 * kp + c] = x3; o[5 * kp + c] = x1;
+      } else {
+        o[c] = x2; o[kp + c] = x1; o[2 * kp + c] = x3;
+        o[3 * kp + c] = x2; o[4 * kp + c] = x1; o[5 * kp + c] = x1;
+      }
+    }
+  }
+}
+// C[m][n] = sum over the nch chunk partials P[c][m][n] (row stride ldp) in
+// chunk order, plus bias[n]
+__global__ void sum_parts_kernel(const float *__restrict__ P, int nch, int M, int N, int ldp,
+                                 const float *__restrict__ bias, float *__restrict__ C, int ldc) {
+  const size_t plane = (size_t)M * ldp;
+  for (int m = blockIdx.x; m < M; m += gridDim.x)
+    for (int n = threadIdx.x; n < N; n += blockDim.x) {
+      float a = bias ? bias[n] : 0.f;
+      for (int c = 0; c < nch; ++c) a += P[c * plane + (size_t)m * ldp + n];
+      C[(size_t)m * ldc + n] = a;
+    }
+}
+}  // namespace
+
+// Reductions longer than this are cut into chunks whose partial products
+// are summed in fp32 afterwards (blocked summation: the tensor cores
+// accumulate a chunk in one fp32 accumulator, and a 32,000-term reduction in
+// one accumulator measured 4e-5 relative against FFMA's blocked 9e-7)
+constexpr int F32X6_KCHUNK = 4096;
+
+bool f32x6_supported(int N, int ldc, const void *C) {
+  return N >= 1 && N % 4 == 0 && ldc % 4 == 0 && (reinterpret_cast<uintptr_t>(C) & 15) == 0 &&
+         encode_fn();
+}
+
+size_t f32x6_scratch_bytes(int M, int N, int K) {
+  const int nch = ceil_div(K, F32X6_KCHUNK);
+  const size_t kp = (size_t)round_up(nch > 1 ? F32X6_KCHUNK : K, 8);
+  size_t b = ((size_t)round_up(M, 8) + (size_t)round_up(N, 8)) * 6 * kp * 2 + 256;
+  if (nch > 1) b += (size_t)nch * M * round_up(N, 4) * 4 + 256;  // the chunk partials
+  return b;
+}
+
+int f32x6_launches(int K) {
+  const int nch = ceil_div(K, F32X6_KCHUNK);
+  return nch > 1 ? 3 * nch + 1 : 3;
+}
+
+cudaError_t launch_gemm_f32x6(const float *A, int lda, const float *B, int ldb, const float *bias,
+                              float *C, int ldc, int M, const int32_t *M_dev, int N, int K,
+                              void *scratch, int nsm, cudaStream_t s, int *err,
+                              uint64_t timeout_ns) {
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  const int nch = ceil_div(K, F32X6_KCHUNK);
+  if (nch > 1 && M_dev) return cudaErrorInvalidValue;  // (a device-side M: short K only)
+  const int kc = nch > 1 ? F32X6_KCHUNK : K, kp = round_up(kc, 8);
+  __nv_bfloat16 *As = reinterpret_cast<__nv_bfloat16 *>(scratch);
+  __nv_bfloat16 *Bs = As + (size_t)round_up(M, 8) * 6 * kp;
+  const int ldp = round_up(N, 4);
+  float *P = reinterpret_cast<float *>(
+      (reinterpret_cast<uintptr_t>(Bs + (size_t)round_up(N, 8) * 6 * kp) + 255) & ~uintptr_t(255));
+  for (int c = 0; c < nch; ++c) {
+    const int k0 = c * kc, kw = std::min(kc, K - k0);
+    // (the split buffers are reused chunk after chunk: stream order puts
+    // each chunk's splits after the previous chunk's GEMM)
+    split3_kernel<<<std::min(M, 65535), 256, 0, s>>>(A + k0, M, kw, lda, As, kp, 0);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    split3_kernel<<<std::min(N, 65535), 256, 0, s>>>(B + k0, N, kw, ldb, Bs, kp, 1);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = nch > 1 ? launch_tc_gemm(As, 6 * kp, Bs, 6 * kp, nullptr, P + (size_t)c * M * ldp, ldp, M,
+                                 nullptr, N, 6 * kp, nsm, s, err, timeout_ns)
+                : launch_tc_gemm(As, 6 * kp, Bs, 6 * kp, bias, C, ldc, M, M_dev, N, 6 * kp, nsm, s,
+                                 err, timeout_ns);
+    if (e != cudaSuccess) return e;
+  }
+  if (nch > 1) {
+    sum_parts_kernel<<<std::min(M, 65535), 256, 0, s>>>(P, nch, M, N, ldp, bias, C, ldc);
+    return cudaGetLastError();
+  }
+  return cudaSuccess;
+}
+
 cudaError_t launch_tc_gemm(const __nv_bfloat16 *X, int ldx, const __nv_bfloat16 *W, int ldw,
                            const float *bias, float *G, int ldg, int M, const int32_t *M_dev,
                            int N, int K, int nsm, cudaStream_t s, int *err, uint64_t timeout_ns) {

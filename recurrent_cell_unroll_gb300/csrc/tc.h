@@ -20,6 +20,23 @@ cudaError_t launch_tc_gemm(const __nv_bfloat16 *X, int ldx, const __nv_bfloat16 
                            const float *bias, float *G, int ldg, int M, const int32_t *M_dev,
                            int N, int K, int nsm, cudaStream_t s, int *err, uint64_t timeout_ns);
 
+// fp32-accurate C = A B^T + bias on the tensor cores for fp32 operands (row
+// strides lda, ldb): each operand is split into three bf16 terms and the six
+// products whose terms carry at least 2^-24 of the result are summed in one
+// bf16 GEMM over a six-segment K, after "Leveraging the bfloat16 artificial
+// intelligence datatype for higher-precision computations" (Henry, Tang,
+// Heinecke, ARITH 2019), the five small products first.  Reductions longer
+// than 4096 are cut into chunks whose fp32 partials are summed afterwards in
+// a fixed order.  It needs f32x6_scratch_bytes of device scratch and
+// f32x6_launches kernels (two splits and a GEMM per chunk, and the sum).
+bool f32x6_supported(int N, int ldc, const void *C);
+size_t f32x6_scratch_bytes(int M, int N, int K);
+int f32x6_launches(int K);
+cudaError_t launch_gemm_f32x6(const float *A, int lda, const float *B, int ldb, const float *bias,
+                              float *C, int ldc, int M, const int32_t *M_dev, int N, int K,
+                              void *scratch, int nsm, cudaStream_t s, int *err,
+                              uint64_t timeout_ns);
+
 // ---- recurrent_tc.cu: persistent recurrent kernel with the per-step
 // h W_hh^T on tcgen05.
 struct TcRecParams {

@@ -443,3 +443,51 @@ def test_gru_training_full_width_sampled_rows():
         print(f"{name}: rel {e:.2e}")
         assert e <= BF16_REL, f"{name}: relative max error {e:.3e}"
     net.close()
+
+
+# fp32 handles with RCU_ATTR_FORCE_PATH = 2: every GEMM (input projection,
+# recomputed pre-activations, weight and input gradients) runs on the tensor
+# cores as a three-term bf16 split at any size; the fp32 bound still holds
+F32X6_SPECS = [
+    wl.LSTM_T80.scaled(T=9, B=13, in_dim=24, hidden=40, h0_std=0.5, c0_std=0.5),
+    wl.GRU_3L.scaled(dtype="f32", layers=2, T=7, B=21, in_dim=36, hidden=52, h0_std=0.5),
+    wl.BILSTM_VAR.scaled(T=12, B=9, in_dim=20, hidden=32, varlen=(1, 12)),
+    # 4,480 rows: the weight gradients' reductions run in two chunks
+    wl.LSTM_T80.scaled(T=70, B=64, in_dim=16, hidden=24),
+]
+
+
+@pytest.mark.parametrize("spec", F32X6_SPECS, ids=_bwd_id)
+def test_fp32_split_tensor_core_gemms(spec):
+    inp = wl.make_rnn_inputs(spec, seed=41)
+    g = torch.Generator().manual_seed(41)
+    dy = torch.randn((spec.T, spec.B, spec.D * spec.Hout), generator=g)
+    dev = torch.device("cuda")
+    net = binding.RNN.from_spec(spec)
+    net.set_weights(inp["weights"])
+    net.set_attr(binding.RCU_ATTR_FORCE_PATH, 2)
+
+    def d(t):
+        return None if t is None else t.to(dev)
+    y, hn, cn = net.forward(d(inp["x"]), lengths=d(inp["lengths"]), h0=d(inp["h0"]),
+                            c0=d(inp["c0"]))
+    dx, dh0, dc0, grads = net.backward(d(inp["x"]), d(dy), lengths=d(inp["lengths"]),
+                                       h0=d(inp["h0"]), c0=d(inp["c0"]))
+    torch.cuda.synchronize()
+    assert net.status() == 0
+    fwd = oracle.rnn_forward(_cell(spec), inp["x"], inp["weights"], hidden=spec.hidden,
+                             bidirectional=spec.bidir, lengths=inp["lengths"], h0=inp["h0"],
+                             c0=inp["c0"])
+    assert float(np.abs(y.cpu().numpy() - fwd[0]).max()) <= 1e-4
+    ref = oracle.rnn_backward(_cell(spec), inp["x"], inp["weights"], dy, hidden=spec.hidden,
+                              bidirectional=spec.bidir, lengths=inp["lengths"], h0=inp["h0"],
+                              c0=inp["c0"])
+    pairs = [("dx", dx, ref["dx"]), ("dh0", dh0, ref["dh0"])]
+    for i in range(spec.layers * spec.D):
+        for k in ("w_ih", "w_hh", "b_ih", "b_hh"):
+            pairs.append((f"d{k}[{i}]", grads[i][k], ref["d" + k][i]))
+    for name, got, want in pairs:
+        e = _rel(got.cpu().numpy().astype(np.float64), want)
+        print(f"{name}: rel {e:.2e}")
+        assert e <= BWD_REL, f"{name}: relative max error {e:.3e}"
+    net.close()
