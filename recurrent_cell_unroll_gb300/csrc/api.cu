@@ -499,11 +499,15 @@ static int ensure_ws(rcu_rnn_s *h, int T, int B) {
 // RCU_ATTR_FORCE_PATH = 1 keeps the FFMA GEMM, 2 takes the split one at any
 // size.  *n counts the kernels launched.
 static constexpr double F32X6_MIN_MACS = 2.0e8;
+static bool use_f32x6(rcu_rnn_t h, int M, const int32_t *M_dev, int N, int K, int ldc,
+                      const void *C) {
+  const bool big = (double)M * N * K >= F32X6_MIN_MACS || h->force_path == 2;
+  return h->force_path != 1 && big && (!M_dev || K <= 4096) && f32x6_supported(N, ldc, C);
+}
 static cudaError_t gemm_f32(rcu_rnn_t h, const float *A, int lda, const float *B, int ldb,
                             const float *bias, float *C, int ldc, int M, const int32_t *M_dev,
                             int N, int K, cudaStream_t s, int *err, int *n) {
-  const bool big = (double)M * N * K >= F32X6_MIN_MACS || h->force_path == 2;
-  if (h->force_path != 1 && big && (!M_dev || K <= 4096) && f32x6_supported(N, ldc, C)) {
+  if (use_f32x6(h, M, M_dev, N, K, ldc, C)) {
     cudaError_t e = h->f32x.ensure(f32x6_scratch_bytes(M, N, K));
     if (e != cudaSuccess) return e;
     *n += f32x6_launches(K);
@@ -819,7 +823,10 @@ extern "C" int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int3
     bool done = false;
     // TMA needs 16-byte row strides: the tensor-core GEMM takes rows of a multiple of 8
     const bool tc_gemm = bf && h->force_path != 1 && (ldx % 8) == 0 && tc_gemm_supported(K, N);
-    h->begin(tc_gemm ? "input_gemm_tc" : "input_gemm_simt", s);
+    h->begin(tc_gemm ? "input_gemm_tc"
+                     : (!bf && use_f32x6(h, Mmax, M_dev, N, K, N, G)) ? "input_gemm_f32x6"
+                                                                      : "input_gemm_simt",
+             s);
     if (tc_gemm) {
       cudaError_t e = launch_tc_gemm((const __nv_bfloat16 *)X, ldx, (const __nv_bfloat16 *)h->wih[l].p,
                                      ldw, (const float *)h->gbias[l].p, G, N, Mmax, M_dev, N, K,

@@ -43,11 +43,24 @@ struct Bars {
   int abort;
 };
 
+// 3-D TMA load of a box at (x, y, z) (a batch of matrices: z = the batch)
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *map, uint64_t *bar,
+                                            int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(tc::smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(tc::smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// BATCH: nb independent products G_b = A_b B_b^T (b < nb, the maps' third
+// dimension; G_b at G + b * strideG), their tiles spread over one launch
+template <bool BATCH>
 __global__ void __launch_bounds__(NT, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const float *__restrict__ bias, float *__restrict__ G, int ldg, int M,
                    const int32_t *__restrict__ M_dev, int N, int K, int *err,
-                   uint64_t timeout_ns) {
+                   uint64_t timeout_ns, int nb, long long strideG) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -58,7 +71,8 @@ __global__ void __launch_bounds__(NT, 1)
 
   if (M_dev) M = *M_dev;
   const int tiles_n = ceil_div(N, BN);
-  const int ntiles = ceil_div(M, BM) * tiles_n;
+  const int ntiles1 = ceil_div(M, BM) * tiles_n;           // tiles of one product
+  const int ntiles = ntiles1 * (BATCH ? nb : 1);
   const int nkb = ceil_div(K, BK);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   volatile int *abort = &bars->abort;
@@ -91,12 +105,18 @@ __global__ void __launch_bounds__(NT, 1)
       int stage = 0;
       uint32_t phase = 0;
       for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-        const int tm = tile / tiles_n, tn = tile % tiles_n;
+        const int bt = tile / ntiles1, t1 = tile % ntiles1;
+        const int tm = t1 / tiles_n, tn = t1 % tiles_n;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!tc::mbar_wait(&bars->empty[stage], phase ^ 1, err, abort, timeout_ns)) goto done;
           tc::mbar_arrive_expect_tx(&bars->full[stage], STAGE_BYTES);
-          tc::tma_load_2d(sA + stage * A_BYTES, &tmA, &bars->full[stage], kb * BK, tm * BM);
-          tc::tma_load_2d(sB + stage * B_BYTES, &tmB, &bars->full[stage], kb * BK, tn * BN);
+          if (BATCH) {
+            tma_load_3d(sA + stage * A_BYTES, &tmA, &bars->full[stage], kb * BK, tm * BM, bt);
+            tma_load_3d(sB + stage * B_BYTES, &tmB, &bars->full[stage], kb * BK, tn * BN, bt);
+          } else {
+            tc::tma_load_2d(sA + stage * A_BYTES, &tmA, &bars->full[stage], kb * BK, tm * BM);
+            tc::tma_load_2d(sB + stage * B_BYTES, &tmB, &bars->full[stage], kb * BK, tn * BN);
+          }
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
       }
@@ -133,7 +153,9 @@ __global__ void __launch_bounds__(NT, 1)
     uint32_t acc_phase = 0;
     const int cl = lane & 7;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-      const int tm = tile / tiles_n, tn = tile % tiles_n;
+      const int bt = tile / ntiles1, t1 = tile % ntiles1;
+      const int tm = t1 / tiles_n, tn = t1 % tiles_n;
+      float *Gb = BATCH ? G + (size_t)bt * strideG : G;
       if (!tc::mbar_wait(&bars->tfull[acc], acc_phase, err, abort, timeout_ns)) goto done;
       tc::tc_fence_after();
       const int row0 = tm * BM + q * 32;
@@ -158,7 +180,7 @@ __global__ void __launch_bounds__(NT, 1)
           float4 f = *reinterpret_cast<const float4 *>(stg + r * 32 + ((cl ^ (r & 7)) * 4));
           f.x += b4.x; f.y += b4.y; f.z += b4.z; f.w += b4.w;
           const int m = row0 + r;
-          if (m < M && n < N) *reinterpret_cast<float4 *>(G + (size_t)m * ldg + n) = f;
+          if (m < M && n < N) *reinterpret_cast<float4 *>(Gb + (size_t)m * ldg + n) = f;
         }
         __syncwarp();
       }
@@ -210,6 +232,60 @@ bool make_map(CUtensorMap *map, const void *base, int rows, int cols, int ld, in
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The same over a batch of nb such matrices, rstride rows apart (3-D map:
+// x = column, y = row, z = batch; box 64 columns x box_rows rows x 1)
+bool make_map_batch(CUtensorMap *map, const void *base, int rows, int cols, int ld,
+                    long long rstride, int nb, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)nb};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)rstride * ld * 2};
+  cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t set_smem_attr() {
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute((const void *)gemm_tc_kernel<false>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute((const void *)gemm_tc_kernel<true>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)SMEM_BYTES);
+  });
+  return attr_err;
+}
+
+// nb products G_b = X_b W_b^T (X_b: rows [b*rsx, b*rsx + M) of X, W_b: rows
+// [b*rsw, b*rsw + N) of W; G_b at G + b*strideG), no bias, in one launch
+cudaError_t launch_tc_gemm_batched(const __nv_bfloat16 *X, int ldx, long long rsx,
+                                   const __nv_bfloat16 *W, int ldw, long long rsw, float *G,
+                                   int ldg, long long strideG, int M, int N, int K, int nb,
+                                   int nsm, cudaStream_t s, int *err, uint64_t timeout_ns) {
+  if (M <= 0 || N <= 0 || nb <= 0) return cudaSuccess;
+  if ((ldx % 8) || (ldw % 8) || (ldg % 4) || (strideG % 4) ||
+      (reinterpret_cast<uintptr_t>(X) % 16) || (reinterpret_cast<uintptr_t>(W) % 16) ||
+      (reinterpret_cast<uintptr_t>(G) % 16))
+    return cudaErrorInvalidValue;
+  CUtensorMap ma, mb;
+  if (!make_map_batch(&ma, X, M, K, ldx, rsx, nb, BM) ||
+      !make_map_batch(&mb, W, N, K, ldw, rsw, nb, BN))
+    return cudaErrorInvalidValue;
+  cudaError_t e = set_smem_attr();
+  if (e != cudaSuccess) return e;
+  const long long tiles = (long long)ceil_div(M, BM) * ceil_div(N, BN) * nb;
+  const int grid = (int)std::min<long long>(tiles, nsm);
+  gemm_tc_kernel<true><<<grid, NT, SMEM_BYTES, s>>>(ma, mb, nullptr, G, ldg, M, nullptr, N, K,
+                                                    err, timeout_ns, nb, strideG);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -275,14 +351,14 @@ bool f32x6_supported(int N, int ldc, const void *C) {
 size_t f32x6_scratch_bytes(int M, int N, int K) {
   const int nch = ceil_div(K, F32X6_KCHUNK);
   const size_t kp = (size_t)round_up(nch > 1 ? F32X6_KCHUNK : K, 8);
-  size_t b = ((size_t)round_up(M, 8) + (size_t)round_up(N, 8)) * 6 * kp * 2 + 256;
+  size_t b = (size_t)nch * ((size_t)round_up(M, 8) + (size_t)round_up(N, 8)) * 6 * kp * 2 + 256;
   if (nch > 1) b += (size_t)nch * M * round_up(N, 4) * 4 + 256;  // the chunk partials
   return b;
 }
 
 int f32x6_launches(int K) {
   const int nch = ceil_div(K, F32X6_KCHUNK);
-  return nch > 1 ? 3 * nch + 1 : 3;
+  return nch > 1 ? 2 * nch + 2 : 3;
 }
 
 cudaError_t launch_gemm_f32x6(const float *A, int lda, const float *B, int ldb, const float *bias,
@@ -293,32 +369,36 @@ cudaError_t launch_gemm_f32x6(const float *A, int lda, const float *B, int ldb, 
   const int nch = ceil_div(K, F32X6_KCHUNK);
   if (nch > 1 && M_dev) return cudaErrorInvalidValue;  // (a device-side M: short K only)
   const int kc = nch > 1 ? F32X6_KCHUNK : K, kp = round_up(kc, 8);
+  const long long Mr = round_up(M, 8), Nr = round_up(N, 8);
+  // chunk c's splits: As rows [c*Mr, c*Mr + M), Bs rows [c*Nr, c*Nr + N)
   __nv_bfloat16 *As = reinterpret_cast<__nv_bfloat16 *>(scratch);
-  __nv_bfloat16 *Bs = As + (size_t)round_up(M, 8) * 6 * kp;
-  const int ldp = round_up(N, 4);
-  float *P = reinterpret_cast<float *>(
-      (reinterpret_cast<uintptr_t>(Bs + (size_t)round_up(N, 8) * 6 * kp) + 255) & ~uintptr_t(255));
+  __nv_bfloat16 *Bs = As + (size_t)nch * Mr * 6 * kp;
   for (int c = 0; c < nch; ++c) {
     const int k0 = c * kc, kw = std::min(kc, K - k0);
-    // (the split buffers are reused chunk after chunk: stream order puts
-    // each chunk's splits after the previous chunk's GEMM)
-    split3_kernel<<<std::min(M, 65535), 256, 0, s>>>(A + k0, M, kw, lda, As, kp, 0);
+    split3_kernel<<<std::min(M, 65535), 256, 0, s>>>(A + k0, M, kw, lda,
+                                                      As + (size_t)c * Mr * 6 * kp, kp, 0);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    split3_kernel<<<std::min(N, 65535), 256, 0, s>>>(B + k0, N, kw, ldb, Bs, kp, 1);
+    split3_kernel<<<std::min(N, 65535), 256, 0, s>>>(B + k0, N, kw, ldb,
+                                                      Bs + (size_t)c * Nr * 6 * kp, kp, 1);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = nch > 1 ? launch_tc_gemm(As, 6 * kp, Bs, 6 * kp, nullptr, P + (size_t)c * M * ldp, ldp, M,
-                                 nullptr, N, 6 * kp, nsm, s, err, timeout_ns)
-                : launch_tc_gemm(As, 6 * kp, Bs, 6 * kp, bias, C, ldc, M, M_dev, N, 6 * kp, nsm, s,
-                                 err, timeout_ns);
-    if (e != cudaSuccess) return e;
   }
-  if (nch > 1) {
-    sum_parts_kernel<<<std::min(M, 65535), 256, 0, s>>>(P, nch, M, N, ldp, bias, C, ldc);
-    return cudaGetLastError();
-  }
-  return cudaSuccess;
+  if (nch == 1)
+    return launch_tc_gemm(As, 6 * kp, Bs, 6 * kp, bias, C, ldc, M, M_dev, N, 6 * kp, nsm, s, err,
+                          timeout_ns);
+  // the chunks' products side by side in one launch (a long reduction over a
+  // small output has too few tiles to fill the GPU on its own), then their
+  // fp32 sum in chunk order
+  const int ldp = round_up(N, 4);
+  float *P = reinterpret_cast<float *>(
+      (reinterpret_cast<uintptr_t>(Bs + (size_t)nch * Nr * 6 * kp) + 255) & ~uintptr_t(255));
+  cudaError_t e = launch_tc_gemm_batched(As, 6 * kp, Mr, Bs, 6 * kp, Nr, P, ldp,
+                                         (long long)M * ldp, M, N, 6 * kp, nch, nsm, s, err,
+                                         timeout_ns);
+  if (e != cudaSuccess) return e;
+  sum_parts_kernel<<<std::min(M, 65535), 256, 0, s>>>(P, nch, M, N, ldp, bias, C, ldc);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_tc_gemm(const __nv_bfloat16 *X, int ldx, const __nv_bfloat16 *W, int ldw,
@@ -331,17 +411,12 @@ cudaError_t launch_tc_gemm(const __nv_bfloat16 *X, int ldx, const __nv_bfloat16 
   CUtensorMap ma, mb;
   if (!make_map(&ma, X, M, K, ldx, BM) || !make_map(&mb, W, N, K, ldw, BN))
     return cudaErrorInvalidValue;
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute((const void *)gemm_tc_kernel,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-  });
-  if (attr_err != cudaSuccess) return attr_err;
+  cudaError_t e = set_smem_attr();
+  if (e != cudaSuccess) return e;
   const long long tiles = (long long)ceil_div(M, BM) * ceil_div(N, BN);
   const int grid = (int)std::min<long long>(tiles, nsm);
-  gemm_tc_kernel<<<grid, NT, SMEM_BYTES, s>>>(ma, mb, bias, G, ldg, M, M_dev, N, K, err,
-                                               timeout_ns);
+  gemm_tc_kernel<false><<<grid, NT, SMEM_BYTES, s>>>(ma, mb, bias, G, ldg, M, M_dev, N, K, err,
+                                                      timeout_ns, 1, 0);
   return cudaGetLastError();
 }
 
