@@ -731,6 +731,9 @@ def run_e2e(args, spec, e2e_io, status, keep, dev, stream, local, device_ms):
     return {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
             "ms_per_step_each": [round(x, 3) for x in per], "steps": e2e_steps,
+            # (the value is the mean; an occasional host-side stall of one call
+            # shows here and in the list)
+            "ms_per_step_median": round(sorted(per)[len(per) // 2], 4),
             "warmup_calls": warm,
             "device_ms_per_step": round(device_ms, 4),
             "link": link,
@@ -1012,7 +1015,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gru", choices=sorted(WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--e2e-steps", type=int, default=5,
+    ap.add_argument("--e2e-steps", type=int, default=10,
                     help="steps of the host-buffer end-to-end leg (0 = skip it)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
