@@ -43,28 +43,48 @@ __global__ void bwd_prep_kernel(int T, int B, int H, int cell, float *__restrict
   const int b = e / H, u = e % H;
   const int nG = cell == CELL_LSTM ? 4 : 3, G = nG * H;
   float c = (cell == CELL_LSTM && c0) ? c0[(size_t)b * H + u] : 0.f;
-  for (int t = 0; t < T; ++t) {
-    const size_t r = (size_t)t * B + b;
-    float *a = zin + r * G;
-    const float *h = zh + r * G;
-    if (cell == CELL_LSTM) {
-      const float i = sigmoid_f(a[u] + h[u]);
-      const float f = sigmoid_f(a[H + u] + h[H + u]);
-      const float g = tanh_f(a[2 * H + u] + h[2 * H + u]);
-      const float o = sigmoid_f(a[3 * H + u] + h[3 * H + u]);
-      c = f * c + i * g;
-      if (cr) {
-        cr[r * H + u] = c;
-        c = fminf(fmaxf(c, clo), chi);
+  // Only c carries from step to step: the pre-activations of SD steps are
+  // loaded before any of them is used, so their memory latencies overlap
+  // (the loop is otherwise one dependent round trip per step).
+  constexpr int SD = 8;
+  for (int t0 = 0; t0 < T; t0 += SD) {
+    float pa[SD][4], ph[SD][4];
+#pragma unroll
+    for (int j = 0; j < SD; ++j) {
+      if (t0 + j >= T) break;
+      const size_t r = (size_t)(t0 + j) * B + b;
+      const float *a = zin + r * G, *h = zh + r * G;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (q >= nG) break;
+        pa[j][q] = a[q * H + u];
+        ph[j][q] = h[q * H + u];
       }
-      cs[r * H + u] = c;
-      if (ms) ms[r * H + u] = o * tanh_f(c);
-      a[u] = i; a[H + u] = f; a[2 * H + u] = g; a[3 * H + u] = o;
-    } else {
-      const float rg = sigmoid_f(a[u] + h[u]);
-      const float z = sigmoid_f(a[H + u] + h[H + u]);
-      const float n = tanh_f(a[2 * H + u] + rg * h[2 * H + u]);
-      a[u] = rg; a[H + u] = z; a[2 * H + u] = n;
+    }
+#pragma unroll
+    for (int j = 0; j < SD; ++j) {
+      if (t0 + j >= T) break;
+      const size_t r = (size_t)(t0 + j) * B + b;
+      float *a = zin + r * G;
+      if (cell == CELL_LSTM) {
+        const float i = sigmoid_f(pa[j][0] + ph[j][0]);
+        const float f = sigmoid_f(pa[j][1] + ph[j][1]);
+        const float g = tanh_f(pa[j][2] + ph[j][2]);
+        const float o = sigmoid_f(pa[j][3] + ph[j][3]);
+        c = f * c + i * g;
+        if (cr) {
+          cr[r * H + u] = c;
+          c = fminf(fmaxf(c, clo), chi);
+        }
+        cs[r * H + u] = c;
+        if (ms) ms[r * H + u] = o * tanh_f(c);
+        a[u] = i; a[H + u] = f; a[2 * H + u] = g; a[3 * H + u] = o;
+      } else {
+        const float rg = sigmoid_f(pa[j][0] + ph[j][0]);
+        const float z = sigmoid_f(pa[j][1] + ph[j][1]);
+        const float n = tanh_f(pa[j][2] + rg * ph[j][2]);
+        a[u] = rg; a[H + u] = z; a[2 * H + u] = n;
+      }
     }
   }
 }
@@ -394,8 +414,8 @@ cudaError_t launch_bwd_prep(int T, int B, int H, int cell, float *zin, const flo
                             const float *c0, float *cs, float *ms, cudaStream_t s, float *cr,
                             float clo, float chi) {
   const int n = B * H;
-  bwd_prep_kernel<<<ceil_div(n, 256), 256, 0, s>>>(T, B, H, cell, zin, zh, c0, cs, ms, cr, clo,
-                                                   chi);
+  bwd_prep_kernel<<<ceil_div(n, 64), 64, 0, s>>>(T, B, H, cell, zin, zh, c0, cs, ms, cr, clo,
+                                                 chi);
   return cudaGetLastError();
 }
 
