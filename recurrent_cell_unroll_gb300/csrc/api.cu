@@ -1186,6 +1186,9 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
   const int M = T * B;
   const size_t TBH = (size_t)M * H, TBO = (size_t)M * Ho, TBY = (size_t)M * DHo,
                TBG = (size_t)M * G;
+  // transposed per-step streams ([rows][ldm8], column t*B + b)
+  const int ldm8 = round_up(M, 8);
+  const bool gru16 = h->dtype == RCU_BF16 && cell == RCU_GRU;
   const int ldh = round_up(H, 8), ldo = round_up(Ho, 8);
   int kmax = std::max(H, DHo);
   for (int l = 0; l < L; ++l) kmax = std::max(kmax, h->in_l[l]);
@@ -1193,8 +1196,11 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
   // ---- workspace (floats; every piece 256-byte aligned)
   size_t off = 0;
   auto take = [&](size_t n) { size_t r = off; off += (n + 63) & ~size_t(63); return r; };
-  const size_t o_keep = take((size_t)L * TBY), o_hp = take(TBO), o_zin = take(TBG),
-               o_zh = take(TBG), o_cs = take(cell == RCU_LSTM ? TBH : 0), o_da = take(TBG),
+  const size_t o_keep = take((size_t)L * TBY), o_hp = take(TBO),
+               // [M][G], or transposed [G][ldm8] for the tcgen05 GRU kernel
+               o_zin = take((size_t)G * ldm8), o_zh = take((size_t)G * ldm8),
+               // that kernel's h_{t-1}^T and dy^T
+               o_hpt = take(gru16 ? (size_t)Ho * ldm8 : 0), o_dyt = take(gru16 ? (size_t)Ho * ldm8 : 0), o_cs = take(cell == RCU_LSTM ? TBH : 0), o_da = take(TBG),
                o_dr = take(cell == RCU_GRU ? TBG : 0), o_dya = take(TBY), o_dyb = take(TBY),
                o_t1 = take(TBG), o_t2 = take(TBK), o_t3 = take(cell == RCU_GRU ? TBG : 0),
                o_t4 = take(TBO), o_wt = take((size_t)kmax * G),
@@ -1214,7 +1220,7 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
                o_cr = take(cell == RCU_LSTM && h->cclip ? TBH : 0),
                o_xm = take(lengths ? (size_t)M * h->in_l[0] : 0),
                // the tcgen05 GRU reverse-time kernel's bias sums [2][batch groups][G]
-               o_bs = take(h->dtype == RCU_BF16 && cell == RCU_GRU ? 2 * (size_t)ceil_div(B, 128) * G : 0),
+               o_bs = take(gru16 ? 2 * (size_t)ceil_div(B, 128) * G : 0),
                o_ctl = take((size_t)std::max(64, tc_bwd_counters(B)));
   CU(h->bw.ensure(off * 4));
   float *wsf = (float *)h->bw.p;
@@ -1230,7 +1236,7 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
   float *XR = wsf + o_xr, *YD = wsf + o_yd, *DYD = wsf + o_dyd, *DXR = wsf + o_dxr,
         *TMP = wsf + o_tmp, *DYM = wsf + o_dym, *XM = wsf + o_xm;
   float *CR = (cell == RCU_LSTM && h->cclip) ? wsf + o_cr : nullptr;
-  float *BS = wsf + o_bs;
+  float *BS = wsf + o_bs, *HPT = wsf + o_hpt, *DYT = wsf + o_dyt;
   unsigned *ctr = (unsigned *)(wsf + o_ctl);
   // bf16 handles: the backward's GEMMs run on the tensor cores like the
   // forward's, on operands rounded to bf16 (the precision of every forward
@@ -1238,7 +1244,7 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
   // RCU_ATTR_FORCE_PATH = 1, keep the fp32 FFMA GEMMs.  bf16 workspace,
   // elements (every piece 256-byte aligned):
   const bool tcg = h->dtype == RCU_BF16 && h->force_path != 1 && tc_gemm_supported(8, 8);
-  const int ldm8 = round_up(M, 8), g8 = round_up(G, 8), k8 = round_up(kmax, 8);
+  const int g8 = round_up(G, 8), k8 = round_up(kmax, 8);
   size_t boff = 0;
   auto btake = [&](size_t n) { size_t r = boff; boff += (n + 127) & ~size_t(127); return r; };
   const size_t b_x = btake(tcg ? (size_t)M * k8 : 0),        // x rows
@@ -1303,10 +1309,29 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
                          cudaMemcpyDeviceToDevice, s));
     // pre-activations of every step
     const bool tcr = tcg && tc_gemm_supported(K, G) && tc_gemm_supported(Ho, G);
+    // the tcgen05 GRU reverse-time kernel (below) activates the gates itself
+    // and reads its per-step inputs transposed
+    const bool tcb = tcg && cell == RCU_GRU && P == 0 && !lengths && tc_bwd_supported(H, B, h->nsm);
     int nl = 0;  // kernels launched by this (layer, direction)
     h->begin("bwd_recompute_gemm", s);
     cudaError_t e = cudaSuccess;
-    if (tcr) {
+    if (tcb) {
+      // (W_ih X^T + b_ih) and (W_hh H_prev^T + b_hh): the same products with
+      // the operands' roles swapped, the biases added per output row
+      __nv_bfloat16 *Xb = bws + b_x, *Hb = bws + b_hp, *Wb = bws + b_whh;
+      e = launch_convert_rows_bf16(X, M, K, K, Xb, ldk, s);
+      if (e == cudaSuccess)
+        e = launch_tc_gemm((const __nv_bfloat16 *)h->wih[l].p + (size_t)d * G * ldk, ldk, Xb, ldk,
+                           (const float *)lw.bih_plain.p, zin, ldm8, G, nullptr, M, K, h->nsm, s,
+                           err, (uint64_t)h->timeout_ns, true);
+      if (e == cudaSuccess) e = launch_convert_rows_bf16(hp, M, Ho, Ho, Hb, ldo, s);
+      if (e == cudaSuccess)
+        e = launch_convert_rows_bf16((const float *)lw.whh_plain.p, G, Ho, ldo, Wb, ldo, s);
+      if (e == cudaSuccess)
+        e = launch_tc_gemm(Wb, ldo, Hb, ldo, (const float *)lw.bhh_plain.p, zh, ldm8, G, nullptr,
+                           M, Ho, h->nsm, s, err, (uint64_t)h->timeout_ns, true);
+      nl += 5;
+    } else if (tcr) {
       // the forward's own operands: bf16 x (or the previous layer's bf16
       // output), bf16 h_{t-1}, the bf16 weights
       __nv_bfloat16 *Xb = bws + b_x, *Hb = bws + b_hp, *Wb = bws + b_whh;
@@ -1331,8 +1356,6 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     }
     h->end(s);
     const float *c0l = c0 ? c0 + (size_t)i * B * H : nullptr;
-    // the tcgen05 GRU reverse-time kernel (below) activates the gates itself
-    const bool tcb = tcg && cell == RCU_GRU && P == 0 && !lengths && tc_bwd_supported(H, B, h->nsm);
     if (!tcb) {
       h->begin("bwd_prep", s);
       if (e == cudaSuccess)
@@ -1382,11 +1405,19 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     const int nbg = ceil_div(B, 128);
     if (tcb) {
       __nv_bfloat16 *WTh = bws + b_wth, *XDR = bws + b_xdr;
+      // h_{t-1}^T and dy^T for the kernel (and with the weight GEMMs on the
+      // tensor cores, H_prev^T in bf16 from the same pass)
+      h->begin("bwd_transpose", s);
+      e = launch_transpose_dual(hp, M, Ho, Ho, HPT, tw ? T4b : nullptr, ldm8, s);
+      if (e == cudaSuccess) e = launch_transpose_dual(rec_dy, M, Ho, Ho, DYT, nullptr, ldm8, s);
+      h->end(s);
+      nl += 2;
       h->begin("bwd_recurrent_tc", s);
-      e = launch_transpose_bf16((const float *)lw.whh_plain.p, G, H, ldo, WTh, g8, s);
+      if (e == cudaSuccess)
+        e = launch_transpose_bf16((const float *)lw.whh_plain.p, G, H, ldo, WTh, g8, s);
       TcBwdParams q{};
       q.T = T; q.B = B; q.H = H;
-      q.zin = zin; q.zh = zh; q.hp = hp; q.dy = rec_dy;
+      q.zin = zin; q.zh = zh; q.hp = HPT; q.dy = DYT; q.ldz = ldm8;
       q.dhn = dhnl;
       if (tcd) {
         q.dat = T1b; q.drt = T3b; q.ldt = ldm8;
@@ -1399,6 +1430,14 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
       q.xdr = XDR; q.Kx = g8; q.wt = WTh;
       q.ctr = ctr; q.err = err; q.timeout_ns = (uint64_t)h->timeout_ns;
       q.drop_arrival = h->drop_arrival == 2 && l == L - 1 && d == 0;
+      if (h->trace && l == 0 && d == 0 && e == cudaSuccess) {
+        // the last reverse-time launch (layer 0) replaces the forward's stamps
+        const size_t rows = (size_t)T + 1;
+        e = h->trace_buf.ensure(rows * 16 * 8);
+        if (e == cudaSuccess) e = cudaMemsetAsync(h->trace_buf.p, 0, rows * 16 * 8, s);
+        h->trace_T = (int)rows;
+        q.trace = (unsigned long long *)h->trace_buf.p;
+      }
       if (e == cudaSuccess) e = launch_tc_bwd(q, h->nsm, s);
       h->end(s);
       if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: recurrence: %s", cudaGetErrorString(e));
@@ -1445,9 +1484,9 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     // to K-contiguous operands), db = column sums; input gradient dX = DA W_ih
     h->begin("bwd_transpose", s);
     if (tcd) {
+      // (H_prev^T came with the reverse-time kernel's inputs)
       e = launch_transpose_bf16(X, M, K, K, T2b, ldm8, s);
-      if (e == cudaSuccess) e = launch_transpose_bf16(hp, M, Ho, Ho, T4b, ldm8, s);
-      nl += 2;
+      nl += 1;
     } else if (tw) {
       e = launch_transpose_bf16(DA, M, G, G, T1b, ldm8, s);
       if (e == cudaSuccess) e = launch_transpose_bf16(X, M, K, K, T2b, ldm8, s);

@@ -333,6 +333,28 @@ __global__ void transpose_kernel(const float *__restrict__ in, int R, int C, int
   }
 }
 
+// out[c][r] = in[r][c] in fp32, and outb[c][r] = bf16(in[r][c]) when outb
+// is given (one read of the input for both)
+__global__ void transpose_dual_kernel(const float *__restrict__ in, int R, int C, int ldi,
+                                      float *__restrict__ out, __nv_bfloat16 *__restrict__ outb,
+                                      int ldo) {
+  __shared__ float tile[32][33];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int r = r0 + i, c = c0 + threadIdx.x;
+    if (r < R && c < C) tile[i][threadIdx.x] = in[(size_t)r * ldi + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int c = c0 + i, r = r0 + threadIdx.x;
+    if (r < R && c < C) {
+      const float v = tile[threadIdx.x][i];
+      out[(size_t)c * ldo + r] = v;
+      if (outb) outb[(size_t)c * ldo + r] = __float2bfloat16_rn(v);
+    }
+  }
+}
+
 // out[r][c] = bf16(in[r][c]) for an R x C row-major matrix (row strides ldi, ldo)
 __global__ void convert_rows_kernel(const float *__restrict__ in, int R, int C, int ldi,
                                     __nv_bfloat16 *__restrict__ out, int ldo) {
@@ -531,6 +553,14 @@ cudaError_t launch_transpose_bf16(const float *in, int R, int C, int ldi, __nv_b
   if (R <= 0 || C <= 0) return cudaSuccess;
   transpose_kernel<__nv_bfloat16><<<dim3(ceil_div(C, 32), ceil_div(R, 32)), dim3(32, 8), 0, s>>>(
       in, R, C, ldi, out, ldo);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_dual(const float *in, int R, int C, int ldi, float *out,
+                                  __nv_bfloat16 *outb, int ldo, cudaStream_t s) {
+  if (R <= 0 || C <= 0) return cudaSuccess;
+  transpose_dual_kernel<<<dim3(ceil_div(C, 32), ceil_div(R, 32)), dim3(32, 8), 0, s>>>(
+      in, R, C, ldi, out, outb, ldo);
   return cudaGetLastError();
 }
 

@@ -123,6 +123,12 @@ __device__ __forceinline__ void st4(float *p, float a, float b, float c, float d
   *reinterpret_cast<float4 *>(p) = make_float4(a, b, c, d);
 }
 
+// Step trace: CTA 0's stamps of reverse step s (row s; slots as documented
+// with rnn_get_trace)
+__device__ __forceinline__ void bstamp(const TcBwdParams &p, int s, int slot) {
+  if (p.trace && blockIdx.x == 0) p.trace[(size_t)s * 16 + slot] = globaltimer_ns();
+}
+
 template <int KS>
 __device__ __forceinline__ void bwd_body(const BMaps &maps, const TcBwdParams &p) {
   static_assert(KS == 2 || KS == 4, "K is split over 2 or 4 CTAs");
@@ -218,6 +224,7 @@ __device__ __forceinline__ void bwd_body(const BMaps &maps, const TcBwdParams &p
           }
           if (!ok) { *abort = 1; break; }
         }
+        bstamp(p, s, 0);
         fence_proxy_async_global();
         const int t1 = T - s;  // dR_{t+1} lives in buffer t1 & 1
         const int arow = (t1 & 1) * B + row0;
@@ -261,11 +268,13 @@ __device__ __forceinline__ void bwd_body(const BMaps &maps, const TcBwdParams &p
         uint64_t bd = bdesc0;
         for (int i = 0; i < nk; ++i, bd += bstep) {
           if (!tc::mbar_wait(&ctl->full[stage], phase, p.err, abort, tmo)) { ok = false; break; }
+          if (i == 0) bstamp(p, s, 1);
           const uint64_t ad = adesc0 + (uint64_t)(stage * (A_STAGE >> 4));
           tc::mma4_bf16_commit(tbase, ad, bd, idesc, i != 0, &ctl->empty[stage]);
           if (++stage == STG) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
+        bstamp(p, s, 2);
         tc::mma_commit(&ctl->tfull);
       }
       // drain: every MMA issued above completes before TMEM is released
@@ -312,21 +321,23 @@ __device__ __forceinline__ void bwd_body(const BMaps &maps, const TcBwdParams &p
     auto load_act = [&](int t) {
       if (!row_ok || t < 0) return;
       const size_t row = (size_t)t * B + b;
-      if (!RCU_DCHECK(row < (size_t)T * B && ub + UPT <= H, p.err)) return;
-      const float *a = p.zin + row * G + ub, *hz = p.zh + row * G + ub;
-      float4 v[8];
-      v[0] = ldg4(a);
-      v[1] = ldg4(a + H);
-      v[2] = ldg4(a + 2 * H);
-      v[3] = ldg4(hz);
-      v[4] = ldg4(hz + H);
-      v[5] = ldg4(hz + 2 * H);
-      v[6] = ldg4(p.hp + row * H + ub);
-      v[7] = ldg4(p.dy + row * H + ub);
+      if (!RCU_DCHECK(row < (size_t)p.ldz && ub + UPT <= H, p.err)) return;
+      // lanes are consecutive batch rows: every load of a warp reads 128
+      // contiguous bytes
+      const size_t ld = (size_t)p.ldz;
+      const float *a = p.zin + (size_t)ub * ld + row, *hz = p.zh + (size_t)ub * ld + row;
+      const float *hq = p.hp + (size_t)ub * ld + row, *dq = p.dy + (size_t)ub * ld + row;
       float f[8][UPT];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        f[k][0] = v[k].x; f[k][1] = v[k].y; f[k][2] = v[k].z; f[k][3] = v[k].w;
+      for (int j = 0; j < UPT; ++j) {
+        f[0][j] = __ldg(a + (size_t)j * ld);
+        f[1][j] = __ldg(a + ((size_t)H + j) * ld);
+        f[2][j] = __ldg(a + ((size_t)2 * H + j) * ld);
+        f[3][j] = __ldg(hz + (size_t)j * ld);
+        f[4][j] = __ldg(hz + ((size_t)H + j) * ld);
+        f[5][j] = __ldg(hz + ((size_t)2 * H + j) * ld);
+        f[6][j] = __ldg(hq + (size_t)j * ld);
+        f[7][j] = __ldg(dq + (size_t)j * ld);
       }
 #pragma unroll
       for (int j = 0; j < UPT; ++j) {
@@ -346,7 +357,10 @@ __device__ __forceinline__ void bwd_body(const BMaps &maps, const TcBwdParams &p
       if (s >= 1) {
         // W_hh^T dR_{t+1}: this CTA's K share from TMEM, the peers' shares
         // of this CTA's units through shared memory
-        if (threadIdx.x == 64) ctl->go = tc::mbar_wait(&ctl->tfull, (uint32_t)(s - 1) & 1u, p.err, abort, tmo);
+        if (threadIdx.x == 64) {
+          ctl->go = tc::mbar_wait(&ctl->tfull, (uint32_t)(s - 1) & 1u, p.err, abort, tmo);
+          bstamp(p, s, 3);
+        }
         epi_bar();
         if (!ctl->go) break;
         tc::tc_fence_after();
@@ -363,11 +377,13 @@ __device__ __forceinline__ void bwd_body(const BMaps &maps, const TcBwdParams &p
                           __uint_as_float(rp[i][1]), __uint_as_float(rp[i][2]),
                           __uint_as_float(rp[i][3]), peer_bar[i]);
         if (threadIdx.x == 64) {
+          bstamp(p, s, 4);
           x_sent = (uint32_t)s;
           tc::mbar_arrive_expect_tx(&ctl->xfull, (uint32_t)geo.x_bytes);
           x_posted = s;
           ctl->go2 = tc::mbar_wait_cluster(&ctl->xfull, (uint32_t)(s - 1) & 1u, p.err, abort, tmo);
           if (ctl->go2) x_done = s;
+          bstamp(p, s, 5);
         }
         epi_bar();
         if (!ctl->go2) break;
@@ -426,8 +442,10 @@ __device__ __forceinline__ void bwd_body(const BMaps &maps, const TcBwdParams &p
       }
       fence_proxy_async_global();
       epi_bar();
-      if (threadIdx.x == 64)
+      if (threadIdx.x == 64) {
         red_release_gpu_add(ctr, (p.drop_arrival && blockIdx.x == 0 && s == 0) ? 0u : 1u);
+        bstamp(p, s, 6);
+      }
       if (row_ok && RCU_DCHECK(row < (size_t)T * B && (!p.dat || row < (size_t)p.ldt), p.err)) {
         // off the critical path: the gate gradients for the GEMMs after the loop
         if (p.DA) {
@@ -460,7 +478,9 @@ __device__ __forceinline__ void bwd_body(const BMaps &maps, const TcBwdParams &p
           }
         }
       }
+      if (threadIdx.x == 64) bstamp(p, s, 7);
       load_act(t - 1);
+      if (threadIdx.x == 64) bstamp(p, s, 8);
     }
     if (threadIdx.x == 64) x_left = x_done < x_posted ? -x_done - 1 : x_done;
     if (p.bsum) {
@@ -558,7 +578,7 @@ cudaError_t launch_tc_bwd(const TcBwdParams &pin, int nsm, cudaStream_t s) {
   int ks = choose_ks(H);
   if (ks == 0) return cudaErrorInvalidValue;
   auto aligned16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
-  if ((p.Kx % 8) || p.Kx < G || !aligned16(p.zin) || !aligned16(p.zh) || !aligned16(p.hp) ||
+  if ((p.Kx % 8) || p.Kx < G || (p.ldz % 4) || p.ldz < p.T * p.B || !aligned16(p.zin) || !aligned16(p.zh) || !aligned16(p.hp) ||
       !aligned16(p.dy) || (p.DA && (!aligned16(p.DA) || !p.DR || !aligned16(p.DR))) ||
       (p.dh0 && !aligned16(p.dh0)) || !aligned16(p.xdr) || !aligned16(p.wt) ||
       (p.dat && (!p.drt || p.ldt < p.T * p.B)) || (p.dab && (!aligned16(p.dab) || (p.ldab % 8) ||

@@ -1,5 +1,5 @@
 // Time-parallel input projection on the 5th-generation tensor cores:
-//   G[m, n] = sum_k X[m, k] * W[n, k] + bias[n]
+//   G[m, n] = sum_k X[m, k] * W[n, k] + bias[n]   (or + bias[m])
 // for all timesteps at once (the "initial input-hidden dense" that "[TOPI] TE
 // implementation of LSTM using scan", apache/tvm PR 11531, names as the first
 // of the LSTM's three dense ops).  bf16 operands, fp32 accumulation in TMEM,
@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(NT, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const float *__restrict__ bias, float *__restrict__ G, int ldg, int M,
                    const int32_t *__restrict__ M_dev, int N, int K, int *err,
-                   uint64_t timeout_ns, int nb, long long strideG) {
+                   uint64_t timeout_ns, int nb, long long strideG, int bias_rows) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -70,8 +70,12 @@ __global__ void __launch_bounds__(NT, 1)
   Bars *bars = reinterpret_cast<Bars *>(smem + STAGES * STAGE_BYTES + EPI_WARPS * STG_FLOATS * 4);
 
   if (M_dev) M = *M_dev;
-  const int tiles_n = ceil_div(N, BN);
-  const int ntiles1 = ceil_div(M, BM) * tiles_n;           // tiles of one product
+  const int tiles_n = ceil_div(N, BN), tiles_m = ceil_div(M, BM);
+  const int ntiles1 = tiles_m * tiles_n;                   // tiles of one product
+  // raster: the operand with fewer tiles varies fastest, so that the CTAs
+  // running at once share the other operand's tiles and the smaller operand
+  // stays in L2 (each tile of the larger one is read once)
+  const bool m_fast = tiles_m < tiles_n;
   const int ntiles = ntiles1 * (BATCH ? nb : 1);
   const int nkb = ceil_div(K, BK);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -106,7 +110,8 @@ __global__ void __launch_bounds__(NT, 1)
       uint32_t phase = 0;
       for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const int bt = tile / ntiles1, t1 = tile % ntiles1;
-        const int tm = t1 / tiles_n, tn = t1 % tiles_n;
+        const int tm = m_fast ? t1 % tiles_m : t1 / tiles_n;
+        const int tn = m_fast ? t1 / tiles_m : t1 % tiles_n;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!tc::mbar_wait(&bars->empty[stage], phase ^ 1, err, abort, timeout_ns)) goto done;
           tc::mbar_arrive_expect_tx(&bars->full[stage], STAGE_BYTES);
@@ -154,7 +159,8 @@ __global__ void __launch_bounds__(NT, 1)
     const int cl = lane & 7;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
       const int bt = tile / ntiles1, t1 = tile % ntiles1;
-      const int tm = t1 / tiles_n, tn = t1 % tiles_n;
+      const int tm = m_fast ? t1 % tiles_m : t1 / tiles_n;
+      const int tn = m_fast ? t1 / tiles_m : t1 % tiles_n;
       float *Gb = BATCH ? G + (size_t)bt * strideG : G;
       if (!tc::mbar_wait(&bars->tfull[acc], acc_phase, err, abort, timeout_ns)) goto done;
       tc::tc_fence_after();
@@ -173,13 +179,14 @@ __global__ void __launch_bounds__(NT, 1)
         __syncwarp();
         const int n = nc + cl * 4;
         float4 b4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (bias && n < N) b4 = *reinterpret_cast<const float4 *>(bias + n);
+        if (bias && !bias_rows && n < N) b4 = *reinterpret_cast<const float4 *>(bias + n);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const int r = i * 4 + (lane >> 3);
           float4 f = *reinterpret_cast<const float4 *>(stg + r * 32 + ((cl ^ (r & 7)) * 4));
-          f.x += b4.x; f.y += b4.y; f.z += b4.z; f.w += b4.w;
           const int m = row0 + r;
+          if (bias_rows && bias && m < M) b4.x = b4.y = b4.z = b4.w = bias[m];
+          f.x += b4.x; f.y += b4.y; f.z += b4.z; f.w += b4.w;
           if (m < M && n < N) *reinterpret_cast<float4 *>(Gb + (size_t)m * ldg + n) = f;
         }
         __syncwarp();
@@ -284,7 +291,7 @@ cudaError_t launch_tc_gemm_batched(const __nv_bfloat16 *X, int ldx, long long rs
   const long long tiles = (long long)ceil_div(M, BM) * ceil_div(N, BN) * nb;
   const int grid = (int)std::min<long long>(tiles, nsm);
   gemm_tc_kernel<true><<<grid, NT, SMEM_BYTES, s>>>(ma, mb, nullptr, G, ldg, M, nullptr, N, K,
-                                                    err, timeout_ns, nb, strideG);
+                                                    err, timeout_ns, nb, strideG, 0);
   return cudaGetLastError();
 }
 
@@ -403,11 +410,15 @@ cudaError_t launch_gemm_f32x6(const float *A, int lda, const float *B, int ldb, 
 
 cudaError_t launch_tc_gemm(const __nv_bfloat16 *X, int ldx, const __nv_bfloat16 *W, int ldw,
                            const float *bias, float *G, int ldg, int M, const int32_t *M_dev,
-                           int N, int K, int nsm, cudaStream_t s, int *err, uint64_t timeout_ns) {
+                           int N, int K, int nsm, cudaStream_t s, int *err, uint64_t timeout_ns,
+                           bool bias_rows) {
   if (M <= 0 || N <= 0) return cudaSuccess;
   if ((ldx % 8) || (ldw % 8) || (ldg % 4) || (reinterpret_cast<uintptr_t>(X) % 16) ||
       (reinterpret_cast<uintptr_t>(W) % 16) || (reinterpret_cast<uintptr_t>(G) % 16))
     return cudaErrorInvalidValue;
+  // the epilogue stores 4 columns at a time: a ragged N needs its row padded
+  // to a multiple of 4 and no per-column bias to read past N
+  if (N % 4 && (ldg < N + (4 - N % 4) || (bias && !bias_rows))) return cudaErrorInvalidValue;
   CUtensorMap ma, mb;
   if (!make_map(&ma, X, M, K, ldx, BM) || !make_map(&mb, W, N, K, ldw, BN))
     return cudaErrorInvalidValue;
@@ -416,7 +427,7 @@ cudaError_t launch_tc_gemm(const __nv_bfloat16 *X, int ldx, const __nv_bfloat16 
   const long long tiles = (long long)ceil_div(M, BM) * ceil_div(N, BN);
   const int grid = (int)std::min<long long>(tiles, nsm);
   gemm_tc_kernel<false><<<grid, NT, SMEM_BYTES, s>>>(ma, mb, bias, G, ldg, M, M_dev, N, K, err,
-                                                      timeout_ns, 1, 0);
+                                                      timeout_ns, 1, 0, bias_rows ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -225,6 +225,9 @@ cudaError_t launch_transpose_bf16(const float *in, int R, int C, int ldi, __nv_b
                                   int ldo, cudaStream_t s);
 cudaError_t launch_convert_rows_bf16(const float *in, int R, int C, int ldi, __nv_bfloat16 *out,
                                      int ldo, cudaStream_t s);
+// the fp32 transpose, and its bf16 rounding too when outb is given (same ldo)
+cudaError_t launch_transpose_dual(const float *in, int R, int C, int ldi, float *out,
+                                  __nv_bfloat16 *outb, int ldo, cudaStream_t s);
 size_t colsum_scratch_floats(int M, int N);
 cudaError_t launch_colsum(const float *A, int M, int N, float *scratch, float *out,
                           cudaStream_t s);

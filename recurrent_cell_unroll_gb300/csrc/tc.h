@@ -15,10 +15,13 @@ namespace rcu {
 
 // ---- gemm_tc.cu: G[m, n] = sum_k X[m, k] W[n, k] + bias[n], bf16 operands,
 // fp32 accumulate in TMEM, fp32 output.  ldx, ldw in elements (multiples of 8).
+// bias_rows: + bias[m] instead (then N needs no multiple of 4 when ldg holds
+// N rounded up to one).
 bool tc_gemm_supported(int K, int N);
 cudaError_t launch_tc_gemm(const __nv_bfloat16 *X, int ldx, const __nv_bfloat16 *W, int ldw,
                            const float *bias, float *G, int ldg, int M, const int32_t *M_dev,
-                           int N, int K, int nsm, cudaStream_t s, int *err, uint64_t timeout_ns);
+                           int N, int K, int nsm, cudaStream_t s, int *err, uint64_t timeout_ns,
+                           bool bias_rows = false);
 
 // fp32-accurate C = A B^T + bias on the tensor cores for fp32 operands (row
 // strides lda, ldb): each operand is split into three bf16 terms and the six
@@ -74,10 +77,14 @@ bool tc_launch_clustered(const void *fn, int grid, int nthreads, int cs, size_t 
 // MMA operand, and finally dh0 = z_0 dh_0 + W_hh^T dR_0.
 struct TcBwdParams {
   int T, B, H;
-  const float *zin;    // [T*B][3H]: input-side pre-activations X W_ih^T + b_ih
-  const float *zh;     // [T*B][3H]: hidden-side pre-activations H_prev W_hh^T + b_hh
-  const float *hp;     // [T*B][H]: h_{t-1}
-  const float *dy;     // [T*B][H]
+  // the per-step inputs, transposed (column t*B + b, row stride ldz, a
+  // multiple of 4 >= T*B) so that a warp's 32 batch rows are 128 contiguous
+  // bytes of one row
+  const float *zin;    // [3H][ldz]: input-side pre-activations (X W_ih^T + b_ih)^T
+  const float *zh;     // [3H][ldz]: hidden-side pre-activations (H_prev W_hh^T + b_hh)^T
+  const float *hp;     // [H][ldz]: h_{t-1}^T
+  const float *dy;     // [H][ldz]: dy^T
+  int ldz;
   const float *dhn;    // [B][H] or NULL
   float *DA, *DR;      // [T*B][3H] fp32, or NULL
   // the same gradients as the tensor-core GEMMs after the loop read them, or
@@ -98,6 +105,7 @@ struct TcBwdParams {
   int *err;
   uint64_t timeout_ns;
   int drop_arrival;
+  unsigned long long *trace;  // NULL, or [T+1][16] global-timer stamps of CTA 0
 };
 bool tc_bwd_supported(int H, int B, int nsm);
 int tc_bwd_counters(int B);

@@ -5,11 +5,14 @@ Runs one workload a few times, then once with the library's step trace on
 CTA 0, resolution about 256 ns) and prints the median time between stamps.
 
     python -m recurrent_cell_unroll_gb300.step_trace --workload gru --T 64 [--ksplit 1]
-        [--all-ctas]
+        [--all-ctas] [--backward]
 
 --all-ctas (tensor-core recurrence): every CTA's stamps for steps 16..23, to
 see how far apart the CTAs publish h_t and how long the last publication
 takes to reach the other CTAs.
+
+--backward (GRU on a bf16 handle): a training pass instead, and the stamps of
+layer 0's tensor-core reverse-time recurrence.
 
 Which stamps exist depends on the kernel that ran (named by the profile):
 tensor-core recurrence, portable SIMT recurrence, cluster-resident
@@ -41,6 +44,14 @@ PHASES = {
     "recurrent_simt": [(0, 3, "h_{t-1} rows loaded"), (3, 4, "mat-vec"),
                        (4, 1, "gates, h_t stored"), (1, 2, "step barrier")],
     "recurrent_cluster": [(0, 3, "mat-vec"), (3, 4, "gates"), (4, 1, "h_t sent")],
+    "bwd_recurrent_tc": [(0, 1, "every dR_{t+1} published -> first stage landed"),
+                         (1, 2, "dR stages streamed, MMAs issued"),
+                         (2, 3, "last MMA issued -> epilogue has the accumulator"),
+                         (3, 4, "accumulator read, partial sums sent"),
+                         (4, 5, "peers' partial sums received"),
+                         (5, 6, "gate gradients, dR_t stored and published"),
+                         (6, 7, "gradient stores for the GEMMs"),
+                         (7, 8, "next step's activations")],
     "rssm": [(0, 5, "actor: ELU layer, tanh layer"), (5, 1, "Linear+ELU on [state, action]"),
              (0, 1, "[actor and] Linear+ELU on [state, action]"), (1, 2, "GRUCell"),
              (2, 3, "Linear+ELU"), (3, 4, "Linear, softplus, sample")],
@@ -92,7 +103,8 @@ def all_cta_summary(rows: np.ndarray):
     return out
 
 
-def run(workload: str, T: int = 0, ksplit: int = 0, seed: int = 0, all_ctas: bool = False):
+def run(workload: str, T: int = 0, ksplit: int = 0, seed: int = 0, all_ctas: bool = False,
+        backward: bool = False):
     spec = WORKLOADS[workload]
     if T > 0:
         kw = {"T": T}
@@ -118,6 +130,8 @@ def run(workload: str, T: int = 0, ksplit: int = 0, seed: int = 0, all_ctas: boo
         tr = binding.rssm_get_trace(m.h, spec.T).numpy().astype(np.float64)
         kernel = "rssm"
     else:
+        if backward:
+            spec = spec.scaled(train=True)
         inp = wl.make_rnn_inputs(spec, seed=seed)
         net = binding.RNN.from_spec(spec)
         if ksplit:
@@ -127,6 +141,27 @@ def run(workload: str, T: int = 0, ksplit: int = 0, seed: int = 0, all_ctas: boo
         h0 = inp["h0"].to(dev) if inp["h0"] is not None else None
         c0 = inp["c0"].to(dev) if inp["c0"] is not None else None
         L = inp["lengths"].to(dev) if inp["lengths"] is not None else None
+        if backward:
+            dy = inp["dy"].to(dev)
+            run1 = lambda: net.backward(x, dy, lengths=L, h0=h0, c0=c0)  # noqa: E731
+            for _ in range(3):
+                run1()
+            net.set_attr(binding.RCU_ATTR_TRACE, 1)
+            net.set_attr(binding.RCU_ATTR_PROFILE, 1)
+            run1()
+            torch.cuda.synchronize()
+            if net.status() != 0:
+                raise RuntimeError("device status after the traced backward")
+            if not any(n.startswith("bwd_recurrent_tc") for n in net.profile()):
+                raise RuntimeError("the backward did not run the tensor-core recurrence")
+            tr = binding.rnn_get_trace(net.h, spec.T + 1).numpy().astype(np.float64)
+            net.close()
+            body = tr[2:max(3, spec.T - 1)]
+            period = float(np.median(np.diff(body[:, 6]))) if len(body) > 1 else float("nan")
+            return {"workload": spec.name, "T": spec.T, "kernel": "bwd_recurrent_tc",
+                    "step_period_ns": period,
+                    "phases_ns": _medians(body, PHASES["bwd_recurrent_tc"]),
+                    "barrier_ns": float(np.median(body[1:, 0] - body[:-1, 6]))}
         for _ in range(3):
             net.forward(x, lengths=L, h0=h0, c0=c0)
         net.set_attr(binding.RCU_ATTR_TRACE, 2 if all_ctas else 1)
@@ -163,8 +198,10 @@ def main(argv=None):
     ap.add_argument("--ksplit", type=int, default=0, choices=[0, 1, 2, 4])
     ap.add_argument("--all-ctas", action="store_true",
                     help="also every CTA's stamps for steps 16..23 (tensor-core kernel)")
+    ap.add_argument("--backward", action="store_true",
+                    help="trace the tensor-core reverse-time recurrence of a training pass")
     args = ap.parse_args(argv)
-    r = run(args.workload, args.T, args.ksplit, all_ctas=args.all_ctas)
+    r = run(args.workload, args.T, args.ksplit, all_ctas=args.all_ctas, backward=args.backward)
     print(f"{r['workload']} T={r['T']} kernel={r['kernel']} "
           f"step period (median) {r['step_period_ns']:.0f} ns")
     for label, v in r["phases_ns"]:
@@ -173,6 +210,8 @@ def main(argv=None):
         c = r["mma_thread_cycles"]
         print(f"  MMA thread clock cycles: issuing {c['issuing']:.0f}, waiting {c['waiting']:.0f}")
         print(f"  {'h_t published -> next step barrier seen':45s} {r['barrier_ns']:8.0f} ns")
+    elif "barrier_ns" in r:
+        print(f"  {'dR_t published -> next step barrier seen':45s} {r['barrier_ns']:8.0f} ns")
     if "all_ctas" in r:
         for k, v in r["all_ctas"].items():
             print(f"  all CTAs: {k:45s} {v}")
