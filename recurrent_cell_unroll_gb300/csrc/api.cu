@@ -1221,7 +1221,9 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
                o_xm = take(lengths ? (size_t)M * h->in_l[0] : 0),
                // the tcgen05 GRU reverse-time kernel's bias sums [2][batch groups][G]
                o_bs = take(gru16 ? 2 * (size_t)ceil_div(B, 128) * G : 0),
-               o_ctl = take((size_t)std::max(64, tc_bwd_counters(B)));
+               o_ctl = take((size_t)std::max(64, tc_bwd_counters(B))),
+               // split-K partials of the tensor-core weight-gradient GEMMs (at most 4 chunks)
+               o_wsk = take(h->dtype == RCU_BF16 ? 4 * (size_t)G * round_up(std::max(kmax, Ho), 4) : 0);
   CU(h->bw.ensure(off * 4));
   float *wsf = (float *)h->bw.p;
   float *keep = wsf + o_keep, *hp = wsf + o_hp, *zin = wsf + o_zin, *zh = wsf + o_zh;
@@ -1236,7 +1238,7 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
   float *XR = wsf + o_xr, *YD = wsf + o_yd, *DYD = wsf + o_dyd, *DXR = wsf + o_dxr,
         *TMP = wsf + o_tmp, *DYM = wsf + o_dym, *XM = wsf + o_xm;
   float *CR = (cell == RCU_LSTM && h->cclip) ? wsf + o_cr : nullptr;
-  float *BS = wsf + o_bs, *HPT = wsf + o_hpt, *DYT = wsf + o_dyt;
+  float *BS = wsf + o_bs, *HPT = wsf + o_hpt, *DYT = wsf + o_dyt, *WSK = wsf + o_wsk;
   unsigned *ctr = (unsigned *)(wsf + o_ctl);
   // bf16 handles: the backward's GEMMs run on the tensor cores like the
   // forward's, on operands rounded to bf16 (the precision of every forward
@@ -1504,12 +1506,16 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     h->end(s);
     h->begin("bwd_weight_gemm", s);
     if (tw) {
+      // (a reduction over all T*B rows into a small output: K split into
+      // chunks summed in order where the output tiles cannot fill the GPU)
+      int n1 = 1, n2 = 1;
       if (e == cudaSuccess)
-        e = launch_tc_gemm(T1b, ldm8, T2b, ldm8, nullptr, gWih, K, G, nullptr, K, M, h->nsm, s,
-                           err, (uint64_t)h->timeout_ns);
+        e = launch_tc_gemm_splitk(T1b, ldm8, T2b, ldm8, nullptr, gWih, K, G, K, M, WSK, h->nsm, s,
+                                  err, (uint64_t)h->timeout_ns, &n1);
       if (e == cudaSuccess)
-        e = launch_tc_gemm(T3b, ldm8, T4b, ldm8, nullptr, gWhh, Ho, G, nullptr, Ho, M, h->nsm, s,
-                           err, (uint64_t)h->timeout_ns);
+        e = launch_tc_gemm_splitk(T3b, ldm8, T4b, ldm8, nullptr, gWhh, Ho, G, Ho, M, WSK, h->nsm,
+                                  s, err, (uint64_t)h->timeout_ns, &n2);
+      nl += n1 + n2 - 2;
     } else {
       if (e == cudaSuccess)
         e = gemm_f32(h, T1, M, T2, M, nullptr, gWih, K, G, nullptr, K, M, s, err, &nl);

@@ -76,8 +76,12 @@ __global__ void __launch_bounds__(NT, 1)
   // running at once share the other operand's tiles and the smaller operand
   // stays in L2 (each tile of the larger one is read once)
   const bool m_fast = tiles_m < tiles_n;
-  const int ntiles = ntiles1 * (BATCH ? nb : 1);
+  // without BATCH, nb > 1 cuts K into nb chunks of nkbc blocks: chunk c's
+  // product goes to G + c * strideG (a split-K partial)
+  const bool ksplit = !BATCH && nb > 1;
+  const int ntiles = ntiles1 * (BATCH || ksplit ? nb : 1);
   const int nkb = ceil_div(K, BK);
+  const int nkbc = ksplit ? ceil_div(nkb, nb) : nkb;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   volatile int *abort = &bars->abort;
 
@@ -112,7 +116,8 @@ __global__ void __launch_bounds__(NT, 1)
         const int bt = tile / ntiles1, t1 = tile % ntiles1;
         const int tm = m_fast ? t1 % tiles_m : t1 / tiles_n;
         const int tn = m_fast ? t1 / tiles_m : t1 % tiles_n;
-        for (int kb = 0; kb < nkb; ++kb) {
+        const int kb0 = ksplit ? bt * nkbc : 0, kb1 = ksplit ? min(nkb, kb0 + nkbc) : nkb;
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!tc::mbar_wait(&bars->empty[stage], phase ^ 1, err, abort, timeout_ns)) goto done;
           tc::mbar_arrive_expect_tx(&bars->full[stage], STAGE_BYTES);
           if (BATCH) {
@@ -135,7 +140,9 @@ __global__ void __launch_bounds__(NT, 1)
         if (!tc::mbar_wait(&bars->tempty[acc], acc_phase ^ 1, err, abort, timeout_ns)) goto done;
         tc::tc_fence_after();
         const uint32_t d = tbase + (uint32_t)(acc * BN);
-        for (int kb = 0; kb < nkb; ++kb) {
+        const int bt = tile / ntiles1;
+        const int kb0 = ksplit ? bt * nkbc : 0, kb1 = ksplit ? min(nkb, kb0 + nkbc) : nkb;
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!tc::mbar_wait(&bars->full[stage], phase, err, abort, timeout_ns)) goto done;
           tc::tc_fence_after();
           const uint32_t a0 = tc::smem_u32(sA + stage * A_BYTES);
@@ -143,7 +150,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             tc::mma_bf16(d, tc::smem_desc_sw128(a0 + kk * 32), tc::smem_desc_sw128(b0 + kk * 32),
-                         idesc, (kb | kk) != 0);
+                         idesc, (kb != kb0 || kk != 0));
           tc::mma_commit(&bars->empty[stage]);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
@@ -161,7 +168,7 @@ __global__ void __launch_bounds__(NT, 1)
       const int bt = tile / ntiles1, t1 = tile % ntiles1;
       const int tm = m_fast ? t1 % tiles_m : t1 / tiles_n;
       const int tn = m_fast ? t1 / tiles_m : t1 % tiles_n;
-      float *Gb = BATCH ? G + (size_t)bt * strideG : G;
+      float *Gb = (BATCH || ksplit) ? G + (size_t)bt * strideG : G;
       if (!tc::mbar_wait(&bars->tfull[acc], acc_phase, err, abort, timeout_ns)) goto done;
       tc::tc_fence_after();
       const int row0 = tm * BM + q * 32;
@@ -405,6 +412,61 @@ cudaError_t launch_gemm_f32x6(const float *A, int lda, const float *B, int ldb, 
                                          timeout_ns);
   if (e != cudaSuccess) return e;
   sum_parts_kernel<<<std::min(M, 65535), 256, 0, s>>>(P, nch, M, N, ldp, bias, C, ldc);
+  return cudaGetLastError();
+}
+
+// K chunks for a long reduction over few output tiles: the count (at most
+// 4) that minimises the waves of tiles times the chunk length, the smallest
+// on a tie; 1 when the tiles fill the GPU or K is short
+int tc_gemm_splitk_chunks(int M, int N, int K, int nsm) {
+  const long long tiles = (long long)ceil_div(M, BM) * ceil_div(N, BN);
+  const int nkb = ceil_div(K, BK);
+  if (nsm < 1 || tiles >= nsm || nkb < 64) return 1;
+  int best = 1;
+  double best_cost = (double)ceil_div(tiles, (long long)nsm);
+  for (int c = 2; c <= 4; ++c) {
+    const int nkbc = ceil_div(nkb, c);
+    if ((c - 1) * nkbc >= nkb) break;  // every chunk holds K blocks
+    const double cost = (double)ceil_div(tiles * c, (long long)nsm) * nkbc / nkb;
+    if (cost < best_cost - 1e-9) { best = c; best_cost = cost; }
+  }
+  return best;
+}
+
+size_t tc_gemm_splitk_scratch_floats(int M, int N, int K, int nsm) {
+  const int c = tc_gemm_splitk_chunks(M, N, K, nsm);
+  return c > 1 ? (size_t)c * M * round_up(N, 4) : 0;
+}
+
+cudaError_t launch_tc_gemm_splitk(const __nv_bfloat16 *X, int ldx, const __nv_bfloat16 *W,
+                                  int ldw, const float *bias, float *G, int ldg, int M, int N,
+                                  int K, float *scratch, int nsm, cudaStream_t s, int *err,
+                                  uint64_t timeout_ns, int *launches) {
+  const int c = tc_gemm_splitk_chunks(M, N, K, nsm);
+  if (c == 1) {
+    if (launches) *launches = 1;
+    return launch_tc_gemm(X, ldx, W, ldw, bias, G, ldg, M, nullptr, N, K, nsm, s, err,
+                          timeout_ns);
+  }
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  const int ldp = round_up(N, 4);
+  if ((ldx % 8) || (ldw % 8) || (reinterpret_cast<uintptr_t>(X) % 16) ||
+      (reinterpret_cast<uintptr_t>(W) % 16) || (reinterpret_cast<uintptr_t>(scratch) % 16))
+    return cudaErrorInvalidValue;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, X, M, K, ldx, BM) || !make_map(&mb, W, N, K, ldw, BN))
+    return cudaErrorInvalidValue;
+  cudaError_t e = set_smem_attr();
+  if (e != cudaSuccess) return e;
+  const long long tiles = (long long)ceil_div(M, BM) * ceil_div(N, BN) * c;
+  const int grid = (int)std::min<long long>(tiles, nsm);
+  gemm_tc_kernel<false><<<grid, NT, SMEM_BYTES, s>>>(ma, mb, nullptr, scratch, ldp, M, nullptr,
+                                                      N, K, err, timeout_ns, c,
+                                                      (long long)M * ldp, 0);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  sum_parts_kernel<<<std::min(M, 65535), 256, 0, s>>>(scratch, c, M, N, ldp, bias, G, ldg);
+  if (launches) *launches = 2;
   return cudaGetLastError();
 }
 

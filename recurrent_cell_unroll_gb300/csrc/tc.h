@@ -23,6 +23,17 @@ cudaError_t launch_tc_gemm(const __nv_bfloat16 *X, int ldx, const __nv_bfloat16 
                            int N, int K, int nsm, cudaStream_t s, int *err, uint64_t timeout_ns,
                            bool bias_rows = false);
 
+// The same product with K cut into chunks when the output tiles alone cannot
+// fill the GPU (a weight gradient: a long reduction over a small output):
+// the chunks' fp32 partials go to scratch (tc_gemm_splitk_scratch_floats)
+// and are summed in chunk order, plus bias[n].  *launches = kernels launched.
+int tc_gemm_splitk_chunks(int M, int N, int K, int nsm);
+size_t tc_gemm_splitk_scratch_floats(int M, int N, int K, int nsm);
+cudaError_t launch_tc_gemm_splitk(const __nv_bfloat16 *X, int ldx, const __nv_bfloat16 *W,
+                                  int ldw, const float *bias, float *G, int ldg, int M, int N,
+                                  int K, float *scratch, int nsm, cudaStream_t s, int *err,
+                                  uint64_t timeout_ns, int *launches);
+
 // fp32-accurate C = A B^T + bias on the tensor cores for fp32 operands (row
 // strides lda, ldb): each operand is split into three bf16 terms and the six
 // products whose terms carry at least 2^-24 of the result are summed in one
