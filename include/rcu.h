@@ -315,14 +315,15 @@ RCU_API int rnn_profile_reset(rcu_rnn_t h);
  * = 2 the tensor-core kernel also stamps every CTA for steps 16 .. 23: row
  * T + i*1024 + c holds the stamps of CTA c at step 16 + i (same slots; rows
  * of CTAs past the grid stay 0), so n_steps up to T + 8192 rows are
- * returned.  After an rnn_backward that ran the tensor-core GRU reverse-time
- * recurrence, the stamps are instead those of layer 0's reverse-time kernel,
- * row s = reverse step s (time step T-1-s), s <= T: 0 producer saw every
- * CTA's dR_{t+1}, 1 first dR stage landed, 2 last MMA issued, 3 epilogue got
- * the accumulator, 4 accumulator read and partial sums sent, 5 peers'
- * partial sums received, 6 dR_t published, 7 gradient stores done, 8 next
- * step's activations ready.  Synchronises the stream.  host_out is host
- * memory.
+ * returned.  After an rnn_backward the stamps are instead those of layer 0's
+ * reverse-time kernel, row s = reverse step s (time step T-1-s), s <= T.
+ * Tensor-core GRU kernel: 0 producer saw every CTA's dR_{t+1}, 1 first dR
+ * stage landed, 2 last MMA issued, 3 epilogue got the accumulator,
+ * 4 accumulator read and partial sums sent, 5 peers' partial sums received,
+ * 6 dR_t published, 7 gradient stores done, 8 next step's activations ready.
+ * FFMA kernel: 0 step start, 1 gate gradients done, 2 step barrier passed,
+ * 3 W_hh^T dR_t done, 4 partial sums reduced.  Synchronises the stream.
+ * host_out is host memory.
  */
 RCU_API int rnn_get_trace(rcu_rnn_t h, int64_t *host_out, int n_steps, void *stream);
 

@@ -1458,6 +1458,14 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     a.dc0 = dc0 ? dc0 + (size_t)i * B * H : nullptr;
     a.ctr = ctr; a.err = err; a.timeout_ns = (uint64_t)h->timeout_ns;
     a.drop_arrival = h->drop_arrival == 2 && l == L - 1 && d == 0;
+    if (!tcb && h->trace && l == 0 && d == 0) {
+      // the last reverse-time launch (layer 0) replaces the forward's stamps
+      const size_t rows = (size_t)T + 1;
+      CU(h->trace_buf.ensure(rows * 16 * 8));
+      CU(cudaMemsetAsync(h->trace_buf.p, 0, rows * 16 * 8, s));
+      h->trace_T = (int)rows;
+      a.trace = (unsigned long long *)h->trace_buf.p;
+    }
     if (!tcb) {
       h->begin("bwd_recurrent", s);
       e = launch_bwd_rec(a, h->nsm, s);

@@ -112,6 +112,7 @@ __device__ __forceinline__ void cp_async_wait() {
 struct BwdParams {
   int T, B, H, cell, U;
   int Gp, KC, KS;     // gate width padded to 4; staged chunk of dR columns; K slices
+  int NB;             // staging buffers (chunks in flight: NB - 1)
   int BS, NUG;        // batch rows per CTA; unit groups (CTA = batch group x unit group)
   const float *Whh;   // [nG*H][ldw], PyTorch row order
   int ldw;
@@ -131,7 +132,13 @@ struct BwdParams {
   int *err;
   uint64_t timeout_ns;
   int drop_arrival;
+  unsigned long long *trace;  // NULL, or stamps of CTA 0 (row = reverse step)
 };
+
+__device__ __forceinline__ void rstamp(const BwdParams &p, int s, int slot) {
+  if (p.trace && blockIdx.x == 0 && threadIdx.x == 0)
+    p.trace[(size_t)s * 16 + slot] = globaltimer_ns();
+}
 
 __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
   extern __shared__ __align__(16) float sm[];
@@ -145,9 +152,11 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
   const int u0 = ug * U, nu = max(0, min(U, H - u0));
   const int Gp = p.Gp, KC = p.KC, KS = p.KS, KCP = KC + 4;
   float *WT = sm;                        // [U][Gp]: WT[j][n] = W_hh[n][u0 + j], zero padded
-  float *xs = WT + (size_t)U * Gp;       // [2][BS][KCP]: staged columns of dR_t (double buffer)
-  float *part = xs + 2 * (size_t)BS * KCP;  // [KS][BS][U]: K-slice partial sums
-  float *dhrec = part + (size_t)KS * BS * U;  // [BS][U]: W_hh^T dR part of dh_t (+ direct GRU path)
+  const int NB = p.NB, PS = BS * U + 1;  // (PS: K-slice stride, padded off a multiple of 32 banks)
+  float *xs = WT + (size_t)U * Gp;       // [NB][BS][KCP]: staged columns of dR_t (ring)
+  float *part = xs + (size_t)NB * BS * KCP;  // K-slice partial sums (rec_part_floats)
+  float *dhrec = part + (KS % 32 == 0 ? (size_t)ceil_div(BS, 4) * (KS / 32) * 64
+                                      : (size_t)KS * PS);  // [BS][U]: W_hh^T dR part of dh_t
   float *dcs = dhrec + (size_t)BS * U;   // [BS][U]: LSTM dc carried to the previous step
   float *dhz = dcs + (size_t)BS * U;     // [BS][U]: GRU z * dh (direct path)
   unsigned *ctr = p.ctr + bgi;
@@ -167,6 +176,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
   const bool vec = (G & 3) == 0;
   const int RG = ceil_div(Bl, 4);
   for (int t = p.T - 1, it = 1; t >= 0; --t, ++it) {
+    rstamp(p, it - 1, 0);
     // ---- gate gradients of this CTA's units at step t
     for (int e = tid; e < Bl * U; e += NT) {
       const int bl = e / U, j = e % U;
@@ -216,10 +226,12 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
         dhz[e] = dh * z;
       }
     }
+    rstamp(p, it - 1, 1);
     // every CTA's gate gradients of step t are published
     if (!group_barrier(ctr, (unsigned)it * p.NUG, p.err, p.timeout_ns,
                        p.drop_arrival && blockIdx.x == 0 && it == 1))
       return;
+    rstamp(p, it - 1, 2);
     // ---- dh_{t-1} of this CTA's units: W_hh^T dR_t (+ z dh).  dR_t is staged
     // in chunks of KC columns with coalesced loads; thread (row group of 4,
     // K slice) keeps a 4 x U register tile and walks the chunk's float4
@@ -234,11 +246,16 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
 #pragma unroll
       for (int j = 0; j < UMAX; ++j) acc[r][j] = 0.f;
     const int nch = ceil_div(Gp, KC);
-    // stage chunk c of dR_t into buffer c & 1: cp.async when rows are 16-byte
-    // aligned (G a multiple of 4), else plain loads
+    // stage chunk c of dR_t into buffer c % NB: cp.async when rows are
+    // 16-byte aligned (G a multiple of 4), else plain loads; one commit group
+    // per call (empty past the last chunk, so the group count stays uniform)
     auto stage = [&](int c) {
+      if (c >= nch) {
+        cp_async_commit();
+        return;
+      }
       const int k0 = c * KC, kc4 = min(KC, Gp - k0) >> 2;
-      float *xb = xs + (size_t)(c & 1) * BS * KCP;
+      float *xb = xs + (size_t)(c % NB) * BS * KCP;
       for (int e = tid; e < Bl * kc4; e += NT) {
         const int b = e / kc4, q = e % kc4, k = k0 + 4 * q;
         const float *src = drt + (size_t)(b0 + b) * G + k;
@@ -256,17 +273,16 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
       }
       cp_async_commit();
     };
-    stage(0);
+    // NB - 1 chunks in flight while one is multiplied
+    for (int c = 0; c < NB - 1; ++c) stage(c);
     for (int c = 0; c < nch; ++c) {
-      if (c + 1 < nch) {
-        stage(c + 1);
-        cp_async_wait<1>();
-      } else {
-        cp_async_wait<0>();
-      }
+      stage(c + NB - 1);  // into the buffer multiplied in the previous round
+      if (NB == 4) cp_async_wait<3>();
+      else if (NB == 3) cp_async_wait<2>();
+      else cp_async_wait<1>();
       __syncthreads();
       const int k0 = c * KC, kc4 = min(KC, Gp - k0) >> 2;
-      const float *xb = xs + (size_t)(c & 1) * BS * KCP;
+      const float *xb = xs + (size_t)(c % NB) * BS * KCP;
       if (comp) {
         for (int q = ksl; q < kc4; q += KS) {
           float4 x[4];
@@ -287,25 +303,67 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
           }
         }
       }
-      __syncthreads();  // buffer c & 1 is refilled by stage(c + 2)
+      __syncthreads();  // buffer c % NB is refilled by stage(c + NB) next round
     }
-    if (comp) {
+    cp_async_wait<0>();  // (only empty groups remain)
+    rstamp(p, it - 1, 3);
+    if (KS % 32 == 0) {
+      // A warp's 32 lanes are 32 K slices of one row group: reduce-scatter
+      // the 4 x 16 tile over the lanes by shuffles (each step keeps half the
+      // values, summed with the partner lane's), so lane l ends with tile
+      // entries sbase(l) and sbase(l) + 1 summed over its warp; then the
+      // row group's KS / 32 warps are summed through shared memory.
+      static_assert(UMAX == 16, "the reduce-scatter walks a 4 x 16 tile");
+      if (comp) {
+        float v[64];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int b = 4 * rg + r;
-        if (b >= Bl) break;
+        for (int i = 0; i < 64; ++i) v[i] = acc[i / 16][i % 16];
+        const int lane = tid & 31;
 #pragma unroll
-        for (int j = 0; j < UMAX; ++j)
-          if (j < U) part[((size_t)ksl * BS + b) * U + j] = acc[r][j];
+        for (int h = 32, m = 16; h >= 2; h >>= 1, m >>= 1) {
+          const bool up = (lane & m) != 0;
+#pragma unroll
+          for (int i = 0; i < h; ++i) {
+            const float send = up ? v[i] : v[i + h];
+            const float keep = up ? v[i + h] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+          }
+        }
+        const int sbase = ((lane >> 4) & 1) * 32 + ((lane >> 3) & 1) * 16 +
+                          ((lane >> 2) & 1) * 8 + ((lane >> 1) & 1) * 4 + (lane & 1) * 2;
+        float *pw = part + (size_t)(rg * (KS / 32) + ksl / 32) * 64;
+        pw[sbase] = v[0];
+        pw[sbase + 1] = v[1];
+      }
+      __syncthreads();
+      const int KW = KS / 32;
+      for (int e = tid; e < Bl * U; e += NT) {
+        const int b = e / U, j = e % U;
+        const float *pr = part + (size_t)(b / 4) * KW * 64 + (b % 4) * 16 + j;
+        float v = 0.f;
+        for (int w = 0; w < KW; ++w) v += pr[(size_t)w * 64];
+        dhrec[e] = (lstm ? 0.f : dhz[e]) + v;
+      }
+    } else {
+      if (comp) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int b = 4 * rg + r;
+          if (b >= Bl) break;
+#pragma unroll
+          for (int j = 0; j < UMAX; ++j)
+            if (j < U) part[(size_t)ksl * PS + b * U + j] = acc[r][j];
+        }
+      }
+      __syncthreads();
+      for (int e = tid; e < Bl * U; e += NT) {
+        float v = 0.f;
+        for (int q = 0; q < KS; ++q) v += part[(size_t)q * PS + e];
+        dhrec[e] = (lstm ? 0.f : dhz[e]) + v;
       }
     }
     __syncthreads();
-    for (int e = tid; e < Bl * U; e += NT) {
-      float v = 0.f;
-      for (int q = 0; q < KS; ++q) v += part[(size_t)q * BS * U + e];
-      dhrec[e] = (lstm ? 0.f : dhz[e]) + v;
-    }
-    __syncthreads();
+    rstamp(p, it - 1, 4);
   }
   for (int e = tid; e < Bl * U; e += NT) {
     const int b = e / U, j = e % U;
@@ -444,9 +502,16 @@ __global__ void colsum_final_kernel(const float *__restrict__ part, int chunks, 
   out[n] = s;
 }
 
-struct RecPlan { int U, Gp, KC, KS, BS, NUG, NBG; size_t smem; };
-size_t rec_smem(int U, int Gp, int BS, int KC, int KS) {
-  return ((size_t)U * Gp + 2 * (size_t)BS * (KC + 4) + (size_t)KS * BS * U + 3 * (size_t)BS * U) *
+struct RecPlan { int U, Gp, KC, KS, BS, NUG, NBG, NB; size_t smem; };
+// partial sums: [KS][BS*U + 1], or with the warp reduce-scatter (KS a
+// multiple of 32) one 4 x 16 tile per warp
+size_t rec_part_floats(int U, int BS, int KS) {
+  return KS % 32 == 0 ? (size_t)ceil_div(BS, 4) * (KS / 32) * 64
+                      : (size_t)KS * ((size_t)BS * U + 1);
+}
+size_t rec_smem(int U, int Gp, int BS, int KC, int KS, int NB) {
+  return ((size_t)U * Gp + (size_t)NB * BS * (KC + 4) + rec_part_floats(U, BS, KS) +
+          3 * (size_t)BS * U) *
          sizeof(float);
 }
 // The grid is NBG batch groups x NUG unit groups (at most one CTA per SM: the
@@ -471,14 +536,32 @@ RecPlan plan_rec(int H, int B, int nG, int nsm) {
     // K slices per row group: as many as the threads allow, halved while the
     // slices' partial tiles (KS * BS * U floats) keep the plan from fitting
     // (the 256-row, 1024-unit GRU fits with 4)
+    // Staging: NB buffers of KC columns, NB - 1 chunks in flight while one
+    // is multiplied; the most columns in flight wins (ties: fewer buffers).
+    // Rings deeper than two need chunks of at least 128 columns.
     bool fits = false;
-    for (r.KS = std::max(1, std::min(32, NT / RG)); r.KS >= 1 && !fits; r.KS /= 2) {
-      r.KC = std::min(512, round_up(r.Gp, 4 * r.KS));
-      while (r.KC > 4 * r.KS && rec_smem(r.U, r.Gp, r.BS, r.KC, r.KS) > SMEM_CAP)
-        r.KC -= 4 * r.KS;
-      r.smem = rec_smem(r.U, r.Gp, r.BS, r.KC, r.KS);
-      fits = r.smem <= SMEM_CAP;
-      if (fits) break;
+    // (up to 16 row groups: every thread, the slices a multiple of 32 so that
+    // a warp holds one row group and sums its slices by shuffles; more row
+    // groups: at most 32 slices summed through shared memory)
+    const int ks0 = RG <= 16 ? (NT / RG) / 32 * 32 : std::max(1, std::min(32, NT / RG));
+    for (r.KS = ks0; r.KS >= 1 && !fits; r.KS /= 2) {
+      int best_score = 0;
+      for (int nb = 2; nb <= 4; ++nb) {
+        int kc = std::min(512, round_up(r.Gp, 4 * r.KS));
+        while (kc > 4 * r.KS && rec_smem(r.U, r.Gp, r.BS, kc, r.KS, nb) > SMEM_CAP) kc -= 4 * r.KS;
+        if (rec_smem(r.U, r.Gp, r.BS, kc, r.KS, nb) > SMEM_CAP) continue;
+        if (nb > 2 && kc < 128) continue;
+        if ((nb - 1) * kc > best_score) {
+          best_score = (nb - 1) * kc;
+          r.NB = nb;
+          r.KC = kc;
+        }
+      }
+      if (best_score > 0) {
+        r.smem = rec_smem(r.U, r.Gp, r.BS, r.KC, r.KS, r.NB);
+        fits = true;
+        break;
+      }
     }
     if (!fits) continue;
     const long long traffic = (long long)nbg * r.NUG * r.BS;
@@ -584,13 +667,14 @@ cudaError_t launch_bwd_rec(const BwdRecArgs &a, int nsm, cudaStream_t s) {
   const int U = rp.U;
   BwdParams p{};
   p.T = a.T; p.B = a.B; p.H = a.H; p.cell = a.cell; p.U = U;
-  p.Gp = rp.Gp; p.KC = rp.KC; p.KS = rp.KS; p.BS = rp.BS; p.NUG = rp.NUG;
+  p.Gp = rp.Gp; p.KC = rp.KC; p.KS = rp.KS; p.BS = rp.BS; p.NUG = rp.NUG; p.NB = rp.NB;
   p.Whh = a.Whh; p.ldw = a.ldw;
   p.gates = a.gates; p.zh = a.zh; p.cs = a.cs; p.c0 = a.c0; p.hp = a.hp;
   p.dy = a.dy; p.dhn = a.dhn; p.dcn = a.dcn; p.lengths = a.lengths;
   p.cr = a.cr; p.clo = a.clo; p.chi = a.chi;
   p.DA = a.DA; p.DR = a.DR; p.dh0 = a.dh0; p.dc0 = a.dc0;
   p.ctr = a.ctr; p.err = a.err; p.timeout_ns = a.timeout_ns; p.drop_arrival = a.drop_arrival;
+  p.trace = a.trace;
   const size_t smem = rp.smem;
   cudaError_t e = cudaFuncSetAttribute((const void *)bwd_rec_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

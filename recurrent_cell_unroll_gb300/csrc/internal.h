@@ -213,6 +213,7 @@ struct BwdRecArgs {
   int *err;
   uint64_t timeout_ns;
   int drop_arrival;  // testing: CTA 0 skips its first step arrival (the wait must run out)
+  unsigned long long *trace;  // NULL, or [T+1][16] global-timer stamps of CTA 0
 };
 // hidden units per CTA of the reverse-time kernel, 0 if W_hh^T does not fit
 int bwd_units_per_cta(int H, int B, int nG, int nsm);

@@ -11,8 +11,9 @@ CTA 0, resolution about 256 ns) and prints the median time between stamps.
 see how far apart the CTAs publish h_t and how long the last publication
 takes to reach the other CTAs.
 
---backward (GRU on a bf16 handle): a training pass instead, and the stamps of
-layer 0's tensor-core reverse-time recurrence.
+--backward: a training pass instead, and the stamps of layer 0's
+reverse-time recurrence (the tensor-core kernel of a bf16 GRU, else the
+FFMA kernel).
 
 Which stamps exist depends on the kernel that ran (named by the profile):
 tensor-core recurrence, portable SIMT recurrence, cluster-resident
@@ -28,7 +29,8 @@ from . import binding
 from . import workloads as wl
 
 WORKLOADS = {"lstm": wl.LSTM_T80, "rssm": wl.RSSM_B50, "lstmp": wl.LSTMP_2L,
-             "bilstm": wl.BILSTM_VAR, "gru": wl.GRU_3L, "rssm_actor": wl.RSSM_ACTOR}
+             "bilstm": wl.BILSTM_VAR, "gru": wl.GRU_3L, "rssm_actor": wl.RSSM_ACTOR,
+             "lstm_train": wl.LSTM_TRAIN, "bilstm_train": wl.BILSTM_TRAIN}
 
 # (from slot, to slot, label) per kernel
 PHASES = {
@@ -52,6 +54,10 @@ PHASES = {
                          (5, 6, "gate gradients, dR_t stored and published"),
                          (6, 7, "gradient stores for the GEMMs"),
                          (7, 8, "next step's activations")],
+    "bwd_recurrent": [(0, 1, "gate gradients of the CTA's units"),
+                      (1, 2, "step barrier"),
+                      (2, 3, "W_hh^T dR_t (dR_t staged from L2)"),
+                      (3, 4, "K-slice partial sums")],
     "rssm": [(0, 5, "actor: ELU layer, tanh layer"), (5, 1, "Linear+ELU on [state, action]"),
              (0, 1, "[actor and] Linear+ELU on [state, action]"), (1, 2, "GRUCell"),
              (2, 3, "Linear+ELU"), (3, 4, "Linear, softplus, sample")],
@@ -152,16 +158,18 @@ def run(workload: str, T: int = 0, ksplit: int = 0, seed: int = 0, all_ctas: boo
             torch.cuda.synchronize()
             if net.status() != 0:
                 raise RuntimeError("device status after the traced backward")
-            if not any(n.startswith("bwd_recurrent_tc") for n in net.profile()):
-                raise RuntimeError("the backward did not run the tensor-core recurrence")
+            kernel = ("bwd_recurrent_tc" if any(n.startswith("bwd_recurrent_tc")
+                                                for n in net.profile()) else "bwd_recurrent")
             tr = binding.rnn_get_trace(net.h, spec.T + 1).numpy().astype(np.float64)
             net.close()
             body = tr[2:max(3, spec.T - 1)]
-            period = float(np.median(np.diff(body[:, 6]))) if len(body) > 1 else float("nan")
-            return {"workload": spec.name, "T": spec.T, "kernel": "bwd_recurrent_tc",
-                    "step_period_ns": period,
-                    "phases_ns": _medians(body, PHASES["bwd_recurrent_tc"]),
-                    "barrier_ns": float(np.median(body[1:, 0] - body[:-1, 6]))}
+            pub = 6 if kernel == "bwd_recurrent_tc" else 0
+            period = float(np.median(np.diff(body[:, pub]))) if len(body) > 1 else float("nan")
+            res = {"workload": spec.name, "T": spec.T, "kernel": kernel,
+                   "step_period_ns": period, "phases_ns": _medians(body, PHASES[kernel])}
+            if kernel == "bwd_recurrent_tc":
+                res["barrier_ns"] = float(np.median(body[1:, 0] - body[:-1, 6]))
+            return res
         for _ in range(3):
             net.forward(x, lengths=L, h0=h0, c0=c0)
         net.set_attr(binding.RCU_ATTR_TRACE, 2 if all_ctas else 1)
