@@ -77,6 +77,28 @@ __host__ __device__ inline Split make_split(int CB, int Rx, int Kx) {
   return s;
 }
 
+// 8 x 4 register tiles for the row-major h rows (below): twice the rows per
+// h load of the 4 x 4 tiles.  K slices: up to 8 (the gates sum them), and no
+// more than let the partial sums [ks][CB][Rx] fit in the h rows' buffer,
+// which they overwrite once the products are done.  tiles = 0: not
+// applicable.
+constexpr int KS8_MAX = 8;
+__host__ __device__ inline Split make_split8(int CB, int Rx, int Kx) {
+  Split s{0, 0, 0};
+  if (CB % 8 != 0 || Rx % 4 != 0 || Rx == 0) return s;
+  const int tiles = (CB / 8) * (Rx / 4);
+  if (tiles == 0 || tiles > NT) return s;
+  int ks = NT / tiles;
+  if (ks > KS8_MAX) ks = KS8_MAX;
+  if (ks > Kx / 4) ks = Kx / 4;
+  if (ks > (Kx + 4) / Rx) ks = (Kx + 4) / Rx;
+  if (ks < 1) return s;
+  s.tiles = tiles;
+  s.ks = ks;
+  s.kc = ceil_div(Kx / 4, ks) * 4;
+  return s;
+}
+
 // red[ks][i][r] = sum over this thread's k range of hs[k][i] * Wsm[k][r]
 template <typename WT>
 __device__ __forceinline__ void chunk_matmul(const WT *Wsm, int Rx, int Kx, const float *hs,
@@ -158,6 +180,56 @@ __device__ __forceinline__ void chunk_matmul_rm(const WT *Wsm, int Rx, int Kx, c
   }
 }
 
+// The same with 8 x 4 tiles (rows ii + i * CB/8), where red aliases hs: every
+// thread of the CTA calls it (a barrier separates the last read of hs from
+// the first store of red).
+template <typename WT>
+__device__ __forceinline__ void chunk_matmul_rm8(const WT *Wsm, int Rx, int Kx, const float *hs,
+                                                 int HS, int CB, float *red, Split sp) {
+  const int tid = threadIdx.x;
+  const bool act = tid < sp.tiles * sp.ks;
+  const int tile = tid % sp.tiles, ks = tid / sp.tiles;
+  const int nrt = Rx / 4;
+  const int ir = tile % nrt, ii = tile / nrt;
+  const int rs = CB / 8;  // row stride between a thread's rows
+  float acc[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  if (act) {
+    const int k0 = ks * sp.kc, k1 = min(Kx, k0 + sp.kc);
+    const float *hp = hs + (size_t)ii * HS;
+    const WT *wp = Wsm + ir * 4;
+#pragma unroll 2
+    for (int k = k0; k < k1; k += 4) {
+      float4 hv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        hv[i] = *reinterpret_cast<const float4 *>(hp + (size_t)i * rs * HS + k);
+      float w[4][4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) load4(wp + (size_t)(k + q) * Rx, w[q]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float h4[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(h4[q], w[q][j], acc[i][j]);
+      }
+    }
+  }
+  __syncthreads();  // hs is dead: red takes its place
+  if (act) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float4 v = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      *reinterpret_cast<float4 *>(red + ((size_t)(ks * CB + ii + i * rs)) * Rx + ir * 4) = v;
+    }
+  }
+}
+
 // hs[k][i] = src[(row0 + i) * ld + k] for i < nr (0 for i >= nr), k < Kx.
 // Loads are issued LB at a time into registers before any store, so their L2
 // latencies overlap.
@@ -199,6 +271,10 @@ struct Smem {
 __host__ __device__ inline bool rowmajor_h(const RecParams &p, size_t wsz) {
   return wsz == 4 && p.proj == 0;
 }
+// ... and multiplied in 8 x 4 tiles whose partial sums reuse the h buffer
+__host__ __device__ inline bool rowmajor_h8(const RecParams &p, size_t wsz) {
+  return rowmajor_h(p, wsz) && make_split8(p.CB, p.Rp, p.Kp).tiles > 0;
+}
 __host__ __device__ inline Smem smem_layout(const RecParams &p, size_t wsz) {
   const bool proj = p.proj > 0;
   Smem L;
@@ -217,6 +293,10 @@ __host__ __device__ inline Smem smem_layout(const RecParams &p, size_t wsz) {
   L.red = o;
   const Split s1 = make_split(p.CB, p.Rp, p.Kp);
   size_t red = (size_t)s1.ks * p.CB * p.Rp;
+  if (rowmajor_h8(p, wsz)) {
+    L.red = L.hs;  // (the partial sums overwrite the h rows)
+    red = 0;
+  }
   if (proj) {
     const Split s2 = make_split(p.CB, p.Pcp, p.Hp);
     red = red > (size_t)s2.ks * p.CB * p.Pcp ? red : (size_t)s2.ks * p.CB * p.Pcp;
@@ -359,7 +439,8 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
   const bool drop = p.drop_arrival && blockIdx.x == 0;
   if (!group_barrier(ctr, ++nbar * p.NU, p.err, p.timeout_ns, drop)) return;
 
-  const Split sp1 = make_split(CB, p.Rp, Kp);
+  const bool rm8 = rowmajor_h8(p, sizeof(WT));
+  const Split sp1 = rm8 ? make_split8(CB, p.Rp, Kp) : make_split(CB, p.Rp, Kp);
   const Split sp2 = proj ? make_split(CB, p.Pcp, Hp) : Split{0, 0, 0};
 
   for (int step = 0; step < p.T; ++step) {
@@ -403,7 +484,10 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
           return;
         }
         if (tr && cb == 0) p.trace[step * 16 + 3] = globaltimer_ns();
-        chunk_matmul_rm(Ws, p.Rp, Kp, hs, Kp + 4, CB, red, sp1);
+        if (rm8)
+          chunk_matmul_rm8(Ws, p.Rp, Kp, hs, Kp + 4, CB, red, sp1);
+        else
+          chunk_matmul_rm(Ws, p.Rp, Kp, hs, Kp + 4, CB, red, sp1);
       } else {
         load_chunk_T(hcur, Kp, cb, nr, Kp, CB, hs);
         __syncthreads();
