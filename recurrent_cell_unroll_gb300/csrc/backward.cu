@@ -21,6 +21,8 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc.h"
+#include "tc_common.cuh"
 
 namespace rcu {
 
@@ -113,6 +115,7 @@ struct BwdParams {
   int T, B, H, cell, U;
   int Gp, KC, KS;     // gate width padded to 4; staged chunk of dR columns; K slices
   int NB;             // staging buffers (chunks in flight: NB - 1)
+  int KP, Gh;         // CTAs splitting K (1 or 2); K columns each holds
   int BS, NUG;        // batch rows per CTA; unit groups (CTA = batch group x unit group)
   const float *Whh;   // [nG*H][ldw], PyTorch row order
   int ldw;
@@ -140,30 +143,49 @@ __device__ __forceinline__ void rstamp(const BwdParams &p, int s, int slot) {
     p.trace[(size_t)s * 16 + slot] = globaltimer_ns();
 }
 
-__global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
+// KP = 1: the CTA holds W_hh^T columns of its own U units over all K = G.
+// KP = 2: a cluster of two CTAs (unit groups 2i, 2i + 1 of one batch group)
+// splits K: each holds the pair's 2U units over its half of K, stages only
+// that half of dR_t (so all of it is in flight at once), and sends the
+// partial sums of the other CTA's units into that CTA's shared memory
+// (st.async, counted on its mbarrier).
+template <int KP>
+__device__ __forceinline__ void bwd_rec_body(const BwdParams &p) {
   extern __shared__ __align__(16) float sm[];
+  __shared__ uint64_t xbar;       // KP = 2: the peer's partial sums of this CTA's units
+  __shared__ unsigned peer_sent;  // KP = 2: steps the peer sent (stored by the peer at exit)
+  __shared__ int s_go, s_abort;
   const int H = p.H, B = p.B, U = p.U;
   const bool lstm = p.cell == CELL_LSTM;
   const int G = (lstm ? 4 : 3) * H;
+  if (KP > 1 && tc::cluster_nctarank() != (uint32_t)KP) {
+    // the K split needs its peer: never address a peer that is not there
+    if (threadIdx.x == 0) atomicCAS(p.err, DEV_OK, DEV_CONFIG);
+    return;
+  }
   // CTA = (batch group bgi: rows [b0, b0 + Bl), unit group ug: units [u0, u0 + nu));
   // batch groups never wait on each other (rows are independent)
   const int BS = p.BS, ug = blockIdx.x % p.NUG, bgi = blockIdx.x / p.NUG;
   const int b0 = bgi * BS, Bl = max(0, min(BS, B - b0));
   const int u0 = ug * U, nu = max(0, min(U, H - u0));
-  const int Gp = p.Gp, KC = p.KC, KS = p.KS, KCP = KC + 4;
-  float *WT = sm;                        // [U][Gp]: WT[j][n] = W_hh[n][u0 + j], zero padded
+  const int kr = KP > 1 ? (ug & 1) : 0;  // this CTA's K share (its rank in the pair)
+  const int pu0 = (ug - kr) * U;         // first unit of the W_hh^T columns held
+  const int Gp = p.Gp, Gh = p.Gh, KC = p.KC, KS = p.KS, KCP = KC + 4;
+  const int kbase = kr * Gh, Kr = max(0, min(Gh, Gp - kbase));  // this CTA's K columns
+  float *WT = sm;  // [KP*U][Gh]: WT[j][n] = W_hh[kbase + n][pu0 + j], zero padded
   const int NB = p.NB, PS = BS * U + 1;  // (PS: K-slice stride, padded off a multiple of 32 banks)
-  float *xs = WT + (size_t)U * Gp;       // [NB][BS][KCP]: staged columns of dR_t (ring)
+  float *xs = WT + (size_t)KP * U * Gh;  // [NB][BS][KCP]: staged columns of dR_t (ring)
   float *part = xs + (size_t)NB * BS * KCP;  // K-slice partial sums (rec_part_floats)
-  float *dhrec = part + (KS % 32 == 0 ? (size_t)ceil_div(BS, 4) * (KS / 32) * 64
+  float *dhrec = part + (KS % 32 == 0 ? (size_t)ceil_div(BS, 4) * KP * (KS / 32) * 64
                                       : (size_t)KS * PS);  // [BS][U]: W_hh^T dR part of dh_t
   float *dcs = dhrec + (size_t)BS * U;   // [BS][U]: LSTM dc carried to the previous step
   float *dhz = dcs + (size_t)BS * U;     // [BS][U]: GRU z * dh (direct path)
+  float *recv = dhz + (size_t)BS * U;    // KP = 2, [BS][U]: the peer's partial sums
   unsigned *ctr = p.ctr + bgi;
   const int tid = threadIdx.x;
-  for (int e = tid; e < U * Gp; e += NT) {
-    const int j = e / Gp, n = e % Gp;
-    WT[e] = (j < nu && n < G) ? p.Whh[(size_t)n * p.ldw + u0 + j] : 0.f;
+  for (int e = tid; e < KP * U * Gh; e += NT) {
+    const int j = e / Gh, n = e % Gh, unit = pu0 + j, k = kbase + n;
+    WT[e] = (unit < H && k < G) ? p.Whh[(size_t)k * p.ldw + unit] : 0.f;
   }
   for (int e = tid; e < BS * U; e += NT) {
     const int b = e / U, j = e % U;
@@ -172,9 +194,25 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
     dcs[e] = (ok && lstm && p.dcn) ? p.dcn[(size_t)(b0 + b) * H + u0 + j] : 0.f;
     dhz[e] = 0.f;
   }
+  uint32_t peer_recv = 0, peer_bar = 0;
+  unsigned x_sent = 0;          // steps whose partial sums this CTA has sent
+  int x_posted = 0, x_done = 0;  // thread 0: receive phases armed / completed
+  if (KP > 1) {
+    if (tid == 0) {
+      tc::mbar_init(&xbar, 1);
+      peer_sent = 0;
+      s_abort = 0;
+      tc::fence_mbar_init();
+    }
+    __syncthreads();
+    tc::cluster_sync();  // the peer's barrier exists before any store into it
+    peer_recv = tc::mapa_shared(tc::smem_u32(recv), (uint32_t)(kr ^ 1));
+    peer_bar = tc::mapa_shared(tc::smem_u32(&xbar), (uint32_t)(kr ^ 1));
+  }
   __syncthreads();
   const bool vec = (G & 3) == 0;
   const int RG = ceil_div(Bl, 4);
+  bool ok = true;
   for (int t = p.T - 1, it = 1; t >= 0; --t, ++it) {
     rstamp(p, it - 1, 0);
     // ---- gate gradients of this CTA's units at step t
@@ -229,23 +267,26 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
     rstamp(p, it - 1, 1);
     // every CTA's gate gradients of step t are published
     if (!group_barrier(ctr, (unsigned)it * p.NUG, p.err, p.timeout_ns,
-                       p.drop_arrival && blockIdx.x == 0 && it == 1))
-      return;
+                       p.drop_arrival && blockIdx.x == 0 && it == 1)) {
+      ok = false;
+      break;
+    }
     rstamp(p, it - 1, 2);
     // ---- dh_{t-1} of this CTA's units: W_hh^T dR_t (+ z dh).  dR_t is staged
     // in chunks of KC columns with coalesced loads; thread (row group of 4,
     // K slice) keeps a 4 x U register tile and walks the chunk's float4
     // columns interleaved by K slice (consecutive threads read consecutive
     // 16-byte words: no bank conflicts); the K-slice partials are summed last.
-    const float *drt = (lstm ? p.DA : p.DR) + (size_t)t * B * G;
-    const int rg = tid / KS, ksl = tid % KS;
+    const float *drt = (lstm ? p.DA : p.DR) + (size_t)t * B * G + kbase;
+    // thread = (row group, unit half of the held columns, K slice)
+    const int rg = tid / (KP * KS), hh = (tid / KS) % KP, ksl = tid % KS;
     const bool comp = rg < RG;
     float acc[4][UMAX];
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
       for (int j = 0; j < UMAX; ++j) acc[r][j] = 0.f;
-    const int nch = ceil_div(Gp, KC);
+    const int nch = ceil_div(Kr, KC);
     // stage chunk c of dR_t into buffer c % NB: cp.async when rows are
     // 16-byte aligned (G a multiple of 4), else plain loads; one commit group
     // per call (empty past the last chunk, so the group count stays uniform)
@@ -254,7 +295,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
         cp_async_commit();
         return;
       }
-      const int k0 = c * KC, kc4 = min(KC, Gp - k0) >> 2;
+      const int k0 = c * KC, kc4 = min(KC, Kr - k0) >> 2;
       float *xb = xs + (size_t)(c % NB) * BS * KCP;
       for (int e = tid; e < Bl * kc4; e += NT) {
         const int b = e / kc4, q = e % kc4, k = k0 + 4 * q;
@@ -263,11 +304,12 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
         if (vec) {
           cp_async16(dst, src);
         } else {
+          const int kg = kbase + k;  // the column in dR_t
           float4 v;
-          v.x = k < G ? __ldcg(src) : 0.f;
-          v.y = k + 1 < G ? __ldcg(src + 1) : 0.f;
-          v.z = k + 2 < G ? __ldcg(src + 2) : 0.f;
-          v.w = k + 3 < G ? __ldcg(src + 3) : 0.f;
+          v.x = kg < G ? __ldcg(src) : 0.f;
+          v.y = kg + 1 < G ? __ldcg(src + 1) : 0.f;
+          v.z = kg + 2 < G ? __ldcg(src + 2) : 0.f;
+          v.w = kg + 3 < G ? __ldcg(src + 3) : 0.f;
           *reinterpret_cast<float4 *>(dst) = v;
         }
       }
@@ -281,8 +323,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
       else if (NB == 3) cp_async_wait<2>();
       else cp_async_wait<1>();
       __syncthreads();
-      const int k0 = c * KC, kc4 = min(KC, Gp - k0) >> 2;
+      const int k0 = c * KC, kc4 = min(KC, Kr - k0) >> 2;
       const float *xb = xs + (size_t)(c % NB) * BS * KCP;
+      const float *wh = WT + (size_t)hh * U * Gh + k0;
       if (comp) {
         for (int q = ksl; q < kc4; q += KS) {
           float4 x[4];
@@ -295,7 +338,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
 #pragma unroll
           for (int j = 0; j < UMAX; ++j) {
             if (j >= U) break;
-            const float4 w = *reinterpret_cast<const float4 *>(WT + (size_t)j * Gp + k0 + 4 * q);
+            const float4 w = *reinterpret_cast<const float4 *>(wh + (size_t)j * Gh + 4 * q);
 #pragma unroll
             for (int r = 0; r < 4; ++r)
               acc[r][j] = fmaf(x[r].x, w.x, fmaf(x[r].y, w.y, fmaf(x[r].z, w.z,
@@ -331,18 +374,43 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
         }
         const int sbase = ((lane >> 4) & 1) * 32 + ((lane >> 3) & 1) * 16 +
                           ((lane >> 2) & 1) * 8 + ((lane >> 1) & 1) * 4 + (lane & 1) * 2;
-        float *pw = part + (size_t)(rg * (KS / 32) + ksl / 32) * 64;
+        float *pw = part + (size_t)((rg * KP + hh) * (KS / 32) + ksl / 32) * 64;
         pw[sbase] = v[0];
         pw[sbase + 1] = v[1];
       }
       __syncthreads();
       const int KW = KS / 32;
-      for (int e = tid; e < Bl * U; e += NT) {
+      // the sum over the warps of (row group, unit half h) for entry e
+      auto psum = [&](int e, int h) {
         const int b = e / U, j = e % U;
-        const float *pr = part + (size_t)(b / 4) * KW * 64 + (b % 4) * 16 + j;
+        const float *pr = part + (size_t)((b / 4) * KP + h) * KW * 64 + (b % 4) * 16 + j;
         float v = 0.f;
         for (int w = 0; w < KW; ++w) v += pr[(size_t)w * 64];
-        dhrec[e] = (lstm ? 0.f : dhz[e]) + v;
+        return v;
+      };
+      if (KP > 1) {
+        // this CTA's sums of the peer's units to the peer (all BS x U
+        // entries: a fixed byte count; rows past Bl are never read)
+        for (int e = tid; e < BS * U; e += NT)
+          tc::st_async_f32(peer_recv + (uint32_t)e * 4u, e < Bl * U ? psum(e, kr ^ 1) : 0.f,
+                           peer_bar);
+        x_sent = (unsigned)it;
+        if (tid == 0) {
+          tc::mbar_arrive_expect_tx(&xbar, (uint32_t)(BS * U * 4));
+          x_posted = it;
+          s_go = tc::mbar_wait_cluster(&xbar, (uint32_t)(it - 1) & 1u, p.err, &s_abort,
+                                       p.timeout_ns);
+          if (s_go) x_done = it;
+        }
+        __syncthreads();
+        if (!s_go) {
+          ok = false;
+          break;
+        }
+        for (int e = tid; e < Bl * U; e += NT)
+          dhrec[e] = (lstm ? 0.f : dhz[e]) + psum(e, kr) + recv[e];
+      } else {
+        for (int e = tid; e < Bl * U; e += NT) dhrec[e] = (lstm ? 0.f : dhz[e]) + psum(e, 0);
       }
     } else {
       if (comp) {
@@ -365,12 +433,39 @@ __global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) {
     __syncthreads();
     rstamp(p, it - 1, 4);
   }
-  for (int e = tid; e < Bl * U; e += NT) {
+  for (int e = tid; ok && e < Bl * U; e += NT) {
     const int b = e / U, j = e % U;
     if (j >= nu) continue;
     if (p.dh0) p.dh0[(size_t)(b0 + b) * H + u0 + j] = dhrec[e];
     if (lstm && p.dc0) p.dc0[(size_t)(b0 + b) * H + u0 + j] = dcs[e];
   }
+  if (KP > 1) {
+    // Exit: tell the peer how many steps of sums it will have received from
+    // this CTA, while it is certainly resident (neither passes the cluster
+    // barrier below before both arrive), then wait (bounded) for a step the
+    // peer sent but this CTA did not consume.  Nothing after the barrier
+    // touches the peer's shared memory.
+    __syncthreads();
+    if (tid == 0) {
+      const uint32_t dst = tc::mapa_shared(tc::smem_u32(&peer_sent), (uint32_t)(kr ^ 1));
+      asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(dst), "r"(x_sent) : "memory");
+    }
+    tc::cluster_sync();
+    if (tid == 0) {
+      const unsigned ps = *reinterpret_cast<volatile unsigned *>(&peer_sent);
+      if ((int)ps > x_done) {
+        if (x_posted == x_done) tc::mbar_arrive_expect_tx(&xbar, (uint32_t)(BS * U * 4));
+        volatile int never = 0;
+        tc::mbar_wait(&xbar, (uint32_t)x_done & 1u, nullptr, &never, 100000000ull);
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) { bwd_rec_body<1>(p); }
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT, 1)
+    bwd_rec_pair_kernel(const BwdParams p) {
+  bwd_rec_body<2>(p);
 }
 
 // out[c][r] = in[r][c] for an R x C row-major matrix (ldi, ldo: row strides),
@@ -502,72 +597,92 @@ __global__ void colsum_final_kernel(const float *__restrict__ part, int chunks, 
   out[n] = s;
 }
 
-struct RecPlan { int U, Gp, KC, KS, BS, NUG, NBG, NB; size_t smem; };
+struct RecPlan { int U, Gp, KC, KS, BS, NUG, NBG, NB, KP, Gh; size_t smem; };
 // partial sums: [KS][BS*U + 1], or with the warp reduce-scatter (KS a
 // multiple of 32) one 4 x 16 tile per warp
-size_t rec_part_floats(int U, int BS, int KS) {
-  return KS % 32 == 0 ? (size_t)ceil_div(BS, 4) * (KS / 32) * 64
+size_t rec_part_floats(int U, int BS, int KS, int KP) {
+  return KS % 32 == 0 ? (size_t)ceil_div(BS, 4) * KP * (KS / 32) * 64
                       : (size_t)KS * ((size_t)BS * U + 1);
 }
-size_t rec_smem(int U, int Gp, int BS, int KC, int KS, int NB) {
-  return ((size_t)U * Gp + (size_t)NB * BS * (KC + 4) + rec_part_floats(U, BS, KS) +
-          3 * (size_t)BS * U) *
+size_t rec_smem(int U, int Gh, int BS, int KC, int KS, int NB, int KP) {
+  return ((size_t)KP * U * Gh + (size_t)NB * BS * (KC + 4) + rec_part_floats(U, BS, KS, KP) +
+          (3 + (KP > 1 ? 1 : 0)) * (size_t)BS * U) *
          sizeof(float);
 }
 // The grid is NBG batch groups x NUG unit groups (at most one CTA per SM: the
 // launch is cooperative).  Every CTA streams its rows of dR_t from L2 each
-// step, NBG * NUG * BS * G floats in all, so more units per CTA (fewer unit
-// groups) means less traffic: the batch is split as far as the register tile
+// step, NBG * NUG * BS * G / KP floats in all, so more units per CTA (fewer
+// unit groups) and a K split over a CTA pair (KP = 2: half the columns per
+// CTA) mean less traffic: the batch is split as far as the register tile
 // (UMAX units) and shared memory (W_hh^T columns, staged chunks of at least
 // 4 * KS columns) allow.  KC: chunk width, a multiple of 4 * KS, at most 512.
-RecPlan plan_rec(int H, int B, int nG, int nsm) {
+// allow_pair = false: KP = 1 only.
+RecPlan plan_rec(int H, int B, int nG, int nsm, bool allow_pair) {
   RecPlan best{};
   long long best_traffic = -1;
   for (int nbg = 1; nbg <= 8 && nbg <= ceil_div(B, 4); nbg *= 2) {
-    RecPlan r{};
-    r.NBG = nbg;
-    r.BS = ceil_div(B, nbg);
-    const int per = std::max(1, std::min(H, nsm / nbg));
-    r.U = ceil_div(H, per);
-    r.NUG = ceil_div(H, r.U);
-    r.Gp = round_up(nG * H, 4);
-    const int RG = ceil_div(r.BS, 4);
-    if (r.U > UMAX || RG > NT || r.NUG * nbg > nsm) continue;
-    // K slices per row group: as many as the threads allow, halved while the
-    // slices' partial tiles (KS * BS * U floats) keep the plan from fitting
-    // (the 256-row, 1024-unit GRU fits with 4)
-    // Staging: NB buffers of KC columns, NB - 1 chunks in flight while one
-    // is multiplied; the most columns in flight wins (ties: fewer buffers).
-    // Rings deeper than two need chunks of at least 128 columns.
-    bool fits = false;
-    // (up to 16 row groups: every thread, the slices a multiple of 32 so that
-    // a warp holds one row group and sums its slices by shuffles; more row
-    // groups: at most 32 slices summed through shared memory)
-    const int ks0 = RG <= 16 ? (NT / RG) / 32 * 32 : std::max(1, std::min(32, NT / RG));
-    for (r.KS = ks0; r.KS >= 1 && !fits; r.KS /= 2) {
-      int best_score = 0;
-      for (int nb = 2; nb <= 4; ++nb) {
-        int kc = std::min(512, round_up(r.Gp, 4 * r.KS));
-        while (kc > 4 * r.KS && rec_smem(r.U, r.Gp, r.BS, kc, r.KS, nb) > SMEM_CAP) kc -= 4 * r.KS;
-        if (rec_smem(r.U, r.Gp, r.BS, kc, r.KS, nb) > SMEM_CAP) continue;
-        if (nb > 2 && kc < 128) continue;
-        if ((nb - 1) * kc > best_score) {
-          best_score = (nb - 1) * kc;
-          r.NB = nb;
-          r.KC = kc;
+    for (int kp = 1; kp <= (allow_pair ? 2 : 1); ++kp) {
+      RecPlan r{};
+      r.NBG = nbg;
+      r.KP = kp;
+      r.BS = ceil_div(B, nbg);
+      const int per = std::max(1, std::min(H, nsm / nbg));
+      if (kp == 1) {
+        r.U = ceil_div(H, per);
+        r.NUG = ceil_div(H, r.U);
+      } else {
+        // pairs of unit groups, 2U units per pair
+        const int pairs = std::max(1, std::min(ceil_div(H, 2), per / 2));
+        r.U = ceil_div(H, 2 * pairs);
+        r.NUG = 2 * ceil_div(H, 2 * r.U);
+      }
+      r.Gp = round_up(nG * H, 4);
+      r.Gh = kp == 1 ? r.Gp : round_up(ceil_div(r.Gp, 2), 4);
+      const int RG = ceil_div(r.BS, 4);
+      if (r.U > UMAX || RG > NT || r.NUG * nbg > nsm) continue;
+      // K split: only with the warp reduce-scatter (a warp = one row group
+      // and unit half), and with a K block for each CTA
+      if (kp > 1 && (RG * kp > 16 || r.Gh >= r.Gp)) continue;
+      // K slices per row group: up to 16 row groups (per unit half), every
+      // thread, the slices a multiple of 32 so that a warp holds one row
+      // group and sums its slices by shuffles; more row groups: at most 32
+      // slices summed through shared memory, halved while their partial
+      // tiles (KS * BS * U floats) keep the plan from fitting (the 256-row,
+      // 1024-unit GRU fits with 4).
+      // Staging: NB buffers of KC columns, NB - 1 chunks in flight while one
+      // is multiplied; the most columns in flight wins, up to all of the
+      // CTA's K columns (ties: fewer buffers).  Rings deeper than two need
+      // chunks of at least 128 columns.
+      bool fits = false;
+      const int ks0 = RG * kp <= 16 ? (NT / (RG * kp)) / 32 * 32
+                                    : std::max(1, std::min(32, NT / RG));
+      for (r.KS = ks0; r.KS >= 1 && !fits; r.KS /= 2) {
+        int best_score = 0;
+        for (int nb = 2; nb <= 4; ++nb) {
+          int kc = std::min(512, round_up(r.Gh, 4 * r.KS));
+          while (kc > 4 * r.KS && rec_smem(r.U, r.Gh, r.BS, kc, r.KS, nb, kp) > SMEM_CAP)
+            kc -= 4 * r.KS;
+          if (rec_smem(r.U, r.Gh, r.BS, kc, r.KS, nb, kp) > SMEM_CAP) continue;
+          if (nb > 2 && kc < 128) continue;
+          const int score = std::min((nb - 1) * kc, round_up(r.Gh, 4 * r.KS));
+          if (score > best_score) {
+            best_score = score;
+            r.NB = nb;
+            r.KC = kc;
+          }
+        }
+        if (best_score > 0) {
+          r.smem = rec_smem(r.U, r.Gh, r.BS, r.KC, r.KS, r.NB, kp);
+          fits = true;
+          break;
         }
       }
-      if (best_score > 0) {
-        r.smem = rec_smem(r.U, r.Gp, r.BS, r.KC, r.KS, r.NB);
-        fits = true;
-        break;
+      if (!fits) continue;
+      const long long traffic = (long long)nbg * r.NUG * r.BS * (kp == 1 ? 2 : 1);
+      if (best_traffic < 0 || traffic < best_traffic) {
+        best = r;
+        best_traffic = traffic;
       }
-    }
-    if (!fits) continue;
-    const long long traffic = (long long)nbg * r.NUG * r.BS;
-    if (best_traffic < 0 || traffic < best_traffic) {
-      best = r;
-      best_traffic = traffic;
     }
   }
   return best;
@@ -658,30 +773,37 @@ cudaError_t launch_add(float *dst, const float *src, size_t n, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-int bwd_units_per_cta(int H, int B, int nG, int nsm) { return plan_rec(H, B, nG, nsm).U; }
+int bwd_units_per_cta(int H, int B, int nG, int nsm) { return plan_rec(H, B, nG, nsm, false).U; }
 
 cudaError_t launch_bwd_rec(const BwdRecArgs &a, int nsm, cudaStream_t s) {
   const int nG = a.cell == CELL_LSTM ? 4 : 3;
-  const RecPlan rp = plan_rec(a.H, a.B, nG, nsm);
-  if (rp.U < 1) return cudaErrorInvalidConfiguration;
-  const int U = rp.U;
-  BwdParams p{};
-  p.T = a.T; p.B = a.B; p.H = a.H; p.cell = a.cell; p.U = U;
-  p.Gp = rp.Gp; p.KC = rp.KC; p.KS = rp.KS; p.BS = rp.BS; p.NUG = rp.NUG; p.NB = rp.NB;
-  p.Whh = a.Whh; p.ldw = a.ldw;
-  p.gates = a.gates; p.zh = a.zh; p.cs = a.cs; p.c0 = a.c0; p.hp = a.hp;
-  p.dy = a.dy; p.dhn = a.dhn; p.dcn = a.dcn; p.lengths = a.lengths;
-  p.cr = a.cr; p.clo = a.clo; p.chi = a.chi;
-  p.DA = a.DA; p.DR = a.DR; p.dh0 = a.dh0; p.dc0 = a.dc0;
-  p.ctr = a.ctr; p.err = a.err; p.timeout_ns = a.timeout_ns; p.drop_arrival = a.drop_arrival;
-  p.trace = a.trace;
-  const size_t smem = rp.smem;
-  cudaError_t e = cudaFuncSetAttribute((const void *)bwd_rec_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  void *args[] = {&p};
-  return cudaLaunchCooperativeKernel((const void *)bwd_rec_kernel, dim3(rp.NBG * rp.NUG),
-                                     dim3(NT), args, smem, s);
+  for (int pass = 0; pass < 2; ++pass) {
+    // the K split over CTA pairs first; without it if that cluster grid
+    // cannot be co-resident
+    const RecPlan rp = plan_rec(a.H, a.B, nG, nsm, pass == 0);
+    if (rp.U < 1) return cudaErrorInvalidConfiguration;
+    if (pass == 1 && rp.KP > 1) return cudaErrorInvalidConfiguration;
+    BwdParams p{};
+    p.T = a.T; p.B = a.B; p.H = a.H; p.cell = a.cell; p.U = rp.U;
+    p.Gp = rp.Gp; p.KC = rp.KC; p.KS = rp.KS; p.BS = rp.BS; p.NUG = rp.NUG; p.NB = rp.NB;
+    p.KP = rp.KP; p.Gh = rp.Gh;
+    p.Whh = a.Whh; p.ldw = a.ldw;
+    p.gates = a.gates; p.zh = a.zh; p.cs = a.cs; p.c0 = a.c0; p.hp = a.hp;
+    p.dy = a.dy; p.dhn = a.dhn; p.dcn = a.dcn; p.lengths = a.lengths;
+    p.cr = a.cr; p.clo = a.clo; p.chi = a.chi;
+    p.DA = a.DA; p.DR = a.DR; p.dh0 = a.dh0; p.dc0 = a.dc0;
+    p.ctr = a.ctr; p.err = a.err; p.timeout_ns = a.timeout_ns; p.drop_arrival = a.drop_arrival;
+    p.trace = a.trace;
+    const size_t smem = rp.smem;
+    const void *fn = rp.KP > 1 ? (const void *)bwd_rec_pair_kernel : (const void *)bwd_rec_kernel;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    void *args[] = {&p};
+    if (rp.KP == 1)
+      return cudaLaunchCooperativeKernel(fn, dim3(rp.NBG * rp.NUG), dim3(NT), args, smem, s);
+    if (tc_launch_clustered(fn, rp.NBG * rp.NUG, NT, 2, smem, args, s, &e)) return e;
+  }
+  return cudaErrorInvalidConfiguration;
 }
 
 // the 64 x 64 vectorised kernel when rows and buffers are aligned for it

@@ -123,6 +123,13 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, flo
       "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
       : "memory");
 }
+// The same for one 4-byte value (4 bytes of complete_tx).
+__device__ __forceinline__ void st_async_f32(uint32_t addr, float a, uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr),
+      "r"(__float_as_uint(a)), "r"(remote_bar)
+      : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
