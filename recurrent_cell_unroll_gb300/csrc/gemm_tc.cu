@@ -316,23 +316,53 @@ namespace {
 // carries the rounding of the K large additions only, as an FFMA loop does.
 // x1 = bf16(x), x2 = bf16(x - x1), x3 = bf16(x - x1 - x2): both residuals
 // are exact in fp32, so x - (x1 + x2 + x3) is within 2^-24 |x|.  Columns past
-// C are written as zero.
-__global__ void split3_kernel(const float *__restrict__ src, int R, int C, int ld,
-                              __nv_bfloat16 *__restrict__ dst, int kp, int pattern) {
+// a chunk's width are written as zero.
+// One launch splits every K chunk of an operand: chunk c = blockIdx.y takes
+// columns [c*kc, min(K, c*kc + kc)) of rows r < R into dst + (c*Rr + r)*6*kp.
+// Each thread splits 8 consecutive columns and writes each of the six
+// segments as one 16-byte store (kp is a multiple of 8).
+__global__ void split3_kernel(const float *__restrict__ src, int R, int K, int ld, int kc,
+                              int Rr, __nv_bfloat16 *__restrict__ dst, int kp, int pattern) {
+  const int ch = blockIdx.y, k0 = ch * kc, kw = min(kc, K - k0);
+  const bool v4 = (ld % 4) == 0 && (k0 % 4) == 0 && (reinterpret_cast<uintptr_t>(src) % 16) == 0;
   for (int r = blockIdx.x; r < R; r += gridDim.x) {
-    __nv_bfloat16 *o = dst + (size_t)r * 6 * kp;
-    for (int c = threadIdx.x; c < kp; c += blockDim.x) {
-      const float x = c < C ? src[(size_t)r * ld + c] : 0.f;
-      const __nv_bfloat16 x1 = __float2bfloat16_rn(x);
-      const float r1 = x - __bfloat162float(x1);
-      const __nv_bfloat16 x2 = __float2bfloat16_rn(r1);
-      const __nv_bfloat16 x3 = __float2bfloat16_rn(r1 - __bfloat162float(x2));
-      if (pattern == 0) {
-        o[c] = x1; o[kp + c] = x2; o[2 * kp + c] = x1;
-        o[3 * kp + c] = x2; o[4 * kp + c] = x3; o[5 * kp + c] = x1;
+    const float *sr = src + (size_t)r * ld + k0;
+    __nv_bfloat16 *o = dst + ((size_t)ch * Rr + r) * 6 * kp;
+    for (int c8 = threadIdx.x * 8; c8 < kp; c8 += blockDim.x * 8) {
+      float x[8];
+      if (v4 && c8 + 8 <= kw) {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(sr + c8));
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(sr + c8 + 4));
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
       } else {
-        o[c] = x2; o[kp + c] = x1; o[2 * kp + c] = x3;
-        o[3 * kp + c] = x2; o[4 * kp + c] = x1; o[5 * kp + c] = x1;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) x[q] = c8 + q < kw ? sr[c8 + q] : 0.f;
+      }
+      uint4 t1, t2, t3;
+      uint32_t *p1 = reinterpret_cast<uint32_t *>(&t1), *p2 = reinterpret_cast<uint32_t *>(&t2),
+               *p3 = reinterpret_cast<uint32_t *>(&t3);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        __nv_bfloat16 a1[2], a2[2], a3[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float v = x[2 * q + h];
+          a1[h] = __float2bfloat16_rn(v);
+          const float r1 = v - __bfloat162float(a1[h]);
+          a2[h] = __float2bfloat16_rn(r1);
+          a3[h] = __float2bfloat16_rn(r1 - __bfloat162float(a2[h]));
+        }
+        p1[q] = (uint32_t)__bfloat16_as_ushort(a1[0]) | ((uint32_t)__bfloat16_as_ushort(a1[1]) << 16);
+        p2[q] = (uint32_t)__bfloat16_as_ushort(a2[0]) | ((uint32_t)__bfloat16_as_ushort(a2[1]) << 16);
+        p3[q] = (uint32_t)__bfloat16_as_ushort(a3[0]) | ((uint32_t)__bfloat16_as_ushort(a3[1]) << 16);
+      }
+      uint4 *ov = reinterpret_cast<uint4 *>(o + c8);
+      const size_t sg = (size_t)kp / 8;  // one segment, in 16-byte units
+      if (pattern == 0) {
+        ov[0] = t1; ov[sg] = t2; ov[2 * sg] = t1; ov[3 * sg] = t2; ov[4 * sg] = t3; ov[5 * sg] = t1;
+      } else {
+        ov[0] = t2; ov[sg] = t1; ov[2 * sg] = t3; ov[3 * sg] = t2; ov[4 * sg] = t1; ov[5 * sg] = t1;
       }
     }
   }
@@ -372,7 +402,7 @@ size_t f32x6_scratch_bytes(int M, int N, int K) {
 
 int f32x6_launches(int K) {
   const int nch = ceil_div(K, F32X6_KCHUNK);
-  return nch > 1 ? 2 * nch + 2 : 3;
+  return nch > 1 ? 4 : 3;
 }
 
 cudaError_t launch_gemm_f32x6(const float *A, int lda, const float *B, int ldb, const float *bias,
@@ -387,14 +417,12 @@ cudaError_t launch_gemm_f32x6(const float *A, int lda, const float *B, int ldb, 
   // chunk c's splits: As rows [c*Mr, c*Mr + M), Bs rows [c*Nr, c*Nr + N)
   __nv_bfloat16 *As = reinterpret_cast<__nv_bfloat16 *>(scratch);
   __nv_bfloat16 *Bs = As + (size_t)nch * Mr * 6 * kp;
-  for (int c = 0; c < nch; ++c) {
-    const int k0 = c * kc, kw = std::min(kc, K - k0);
-    split3_kernel<<<std::min(M, 65535), 256, 0, s>>>(A + k0, M, kw, lda,
-                                                      As + (size_t)c * Mr * 6 * kp, kp, 0);
+  {
+    const int thr = std::min(256, round_up(kp / 8, 32));
+    split3_kernel<<<dim3(std::min(M, 65535), nch), thr, 0, s>>>(A, M, K, lda, kc, (int)Mr, As, kp, 0);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    split3_kernel<<<std::min(N, 65535), 256, 0, s>>>(B + k0, N, kw, ldb,
-                                                      Bs + (size_t)c * Nr * 6 * kp, kp, 1);
+    split3_kernel<<<dim3(std::min(N, 65535), nch), thr, 0, s>>>(B, N, K, ldb, kc, (int)Nr, Bs, kp, 1);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -42,7 +42,8 @@ cudaError_t launch_tc_gemm_splitk(const __nv_bfloat16 *X, int ldx, const __nv_bf
 // Heinecke, ARITH 2019), the five small products first.  Reductions longer
 // than 4096 are cut into chunks whose fp32 partials are summed afterwards in
 // a fixed order.  It needs f32x6_scratch_bytes of device scratch and
-// f32x6_launches kernels (two splits and a GEMM per chunk, and the sum).
+// f32x6_launches kernels (the two operands' splits, the GEMM, and with
+// several chunks the ordered sum).
 bool f32x6_supported(int N, int ldc, const void *C);
 size_t f32x6_scratch_bytes(int M, int N, int K);
 int f32x6_launches(int K);
