@@ -61,6 +61,13 @@ BWD_SPECS = [
     wl.LSTMP_2L.scaled(T=7, B=5, in_dim=8, hidden=16, proj=6, dtype="f32", bidir=True,
                        varlen=(1, 7), h0_std=0.5),
     wl.BILSTM_VAR.scaled(T=40, B=64, in_dim=256, hidden=256, varlen=(5, 40)),
+    # batches too large for the reverse-time kernel's K split over a CTA pair
+    # (which needs at most 32 rows per batch group): single CTAs, the K slices
+    # summed by warp shuffles (38 rows per group) ...
+    wl.GRU_3L.scaled(T=4, B=300, in_dim=16, hidden=24, layers=1, dtype="f32", h0_std=0.3),
+    # ... and through shared memory (75 rows per group: more than 16 row
+    # groups, 26 slices)
+    wl.LSTM_T80.scaled(T=3, B=600, in_dim=12, hidden=20, layers=1, h0_std=0.5, c0_std=0.5),
 ]
 
 
@@ -123,6 +130,9 @@ BWD_BF16_SPECS = [
     # input width 13: the weight-gradient GEMMs keep the fp32 path (their
     # output rows need a multiple of 4), the recompute runs on the tensor cores
     wl.LSTM_T80.scaled(T=6, B=20, in_dim=13, hidden=48, dtype="bf16", h0_std=0.5, c0_std=0.5),
+    # T*B = 4096 rows: the weight-gradient GEMMs (2 output tiles against
+    # 64 K blocks) split K into 4 chunks summed in order
+    wl.GRU_3L.scaled(T=64, B=64, in_dim=32, hidden=64, layers=2, h0_std=0.5),
 ]
 
 
