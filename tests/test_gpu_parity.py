@@ -470,13 +470,13 @@ def test_barrier_timeout_on_tensor_core_path(ksplit):
     net.close()
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_backward_recurrence_timeout(dtype):
-    """A CTA of the reverse-time kernel (FFMA for fp32; tcgen05 for the bf16
-    GRU) skips its first step arrival: the bounded counter wait runs out, the
-    status reads RCU_ERR_TIMEOUT, and the next backward on the same handle is
-    correct."""
-    spec = wl.GRU_3L.scaled(T=6, B=9, in_dim=16, hidden=24 if dtype == "f32" else 64, layers=2,
+@pytest.mark.parametrize("dtype,B", [("f32", 9), ("f32", 300), ("bf16", 9)])
+def test_backward_recurrence_timeout(dtype, B):
+    """A CTA of the reverse-time kernel (FFMA for fp32: its CTA-pair K split
+    at 9 rows, single CTAs at 300; tcgen05 for the bf16 GRU) skips its first
+    step arrival: the bounded counter wait runs out, the status reads
+    RCU_ERR_TIMEOUT, and the next backward on the same handle is correct."""
+    spec = wl.GRU_3L.scaled(T=6, B=B, in_dim=16, hidden=24 if dtype == "f32" else 64, layers=2,
                             dtype=dtype)
     inp = wl.make_rnn_inputs(spec, seed=15)
     dy = torch.randn((spec.T, spec.B, spec.hidden), generator=torch.Generator().manual_seed(15))
