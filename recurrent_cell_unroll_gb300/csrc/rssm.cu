@@ -86,7 +86,7 @@ __host__ __device__ inline int split_of(int Op, int K) {
 
 // shared-memory carve-up (floats)
 struct Layout {
-  size_t w1, b1, wih, whh, bih, bhh, w2, b2, w3, b3;  // weights (transposed [k][o], o padded)
+  size_t w1, b1, wih, whh, bih, bhh, w2, b2, w3, b3;  // weights ([o][k], both padded)
   size_t wa1, ba1, wa2, ba2;                           // actor weights (same form)
   size_t st, in1, av, bel, qv;                         // vectors, [Bc][padded width]
   size_t ain, hx;                                      // actor input [state, belief], hidden
@@ -99,19 +99,21 @@ __host__ __device__ inline Layout make_layout(const Dims &d, int T) {
   Layout L;
   size_t o = 0;
   auto take = [&](size_t n) { size_t r = o; o += (n + 3) & ~size_t(3); return r; };
-  L.w1 = take((size_t)(d.S + d.A) * d.Hap);
+  // weights [o][k] (the outputs this CTA owns, rows padded to a multiple of
+  // 4; k padded likewise)
+  L.w1 = take((size_t)d.Hap * d.SAp);
   L.b1 = take(d.Hap);
-  L.wih = take((size_t)d.Hd * d.U3p);
-  L.whh = take((size_t)d.RH * d.U3p);
+  L.wih = take((size_t)d.U3p * d.Hdp);
+  L.whh = take((size_t)d.U3p * d.RHp);
   L.bih = take(d.U3p);
   L.bhh = take(d.U3p);
-  L.w2 = take((size_t)d.RH * d.Hap);
+  L.w2 = take((size_t)d.Hap * d.RHp);
   L.b2 = take(d.Hap);
-  L.w3 = take((size_t)d.Hd * d.S2p);
+  L.w3 = take((size_t)d.S2p * d.Hdp);
   L.b3 = take(d.S2p);
-  L.wa1 = take(d.Hx > 0 ? (size_t)(d.S + d.RH) * d.Hxap : 0);
+  L.wa1 = take(d.Hx > 0 ? (size_t)d.Hxap * d.SRp : 0);
   L.ba1 = take(d.Hx > 0 ? d.Hxap : 0);
-  L.wa2 = take(d.Hx > 0 ? (size_t)d.Hx * d.Axap : 0);
+  L.wa2 = take(d.Hx > 0 ? (size_t)d.Axap * d.Hxp : 0);
   L.ba2 = take(d.Hx > 0 ? d.Axap : 0);
   L.st = take((size_t)d.Bc * d.S);
   L.in1 = take((size_t)d.Bc * d.SAp);
@@ -205,6 +207,93 @@ __device__ __forceinline__ void matvec_part(const float *Wt, int Op, int K, cons
   }
 }
 
+// out[r*Op + o] = sum over k < K of Wo[o*ldw + k] * V[r*ldv + k], for o < Op
+// (a multiple of 4), r < NR.  Threads [t0, t0 + nthr) (nthr a multiple of
+// 32) take part: SL consecutive lanes share a group of 4 outputs and split K
+// between them (lane l: columns 4l, 4l + 4*SL, ...; every load 16 bytes at
+// consecutive addresses across the lanes, and the weights [o][k] rows, so no
+// bank conflicts), then sum their 4 x NR partials by a shuffle
+// reduce-scatter that leaves each lane whole sums to store.  No shared-memory
+// partials and no CTA barrier inside; ldw and ldv are multiples of 4, the
+// weights' columns from K up to ldw are zero, and V's are not read.
+template <int NR, int SL>
+__device__ __forceinline__ void matvec_sl(const float *Wo, int ldw, int Op, int K,
+                                          const float *V, int ldv, float *out, int t0, int nthr) {
+  static_assert(SL == 8 || SL == 16, "8 or 16 lanes per output group");
+  constexpr int NV = 4 * NR;
+  constexpr int PER0 = (NV + SL - 1) / SL;
+  constexpr int PER = PER0 <= 1 ? 1 : (PER0 <= 2 ? 2 : (PER0 <= 4 ? 4 : 8));  // sums per lane
+  constexpr int NVP = SL * PER;
+  const int t = threadIdx.x - t0;
+  if (t < 0 || t >= nthr) return;  // (whole warps: t0 and nthr are multiples of 32)
+  const int ng = Op / 4, slots = nthr / SL;
+  const int slot = t / SL, l = t % SL, lane = threadIdx.x & 31;
+  const int wslot0 = (t / 32) * (32 / SL);  // this warp's first slot
+  const int K4 = (K + 3) & ~3;
+  for (int base = 0; base < ng; base += slots) {
+    if (base + wslot0 >= ng) break;  // no group of this warp left (warp-uniform)
+    const int og = base + slot;
+    const bool valid = og < ng;
+    float a[NR][4];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) a[r][0] = a[r][1] = a[r][2] = a[r][3] = 0.f;
+    if (valid) {
+      const float *w0 = Wo + (size_t)og * 4 * ldw;
+      for (int k = 4 * l; k < K4; k += 4 * SL) {
+        float4 w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = *reinterpret_cast<const float4 *>(w0 + (size_t)i * ldw + k);
+        const int rem = K - k;  // (>= 1; below 4 in the last chunk only)
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+          float4 v = *reinterpret_cast<const float4 *>(V + (size_t)r * ldv + k);
+          if (rem < 4) {  // the row's padding may hold another phase's values
+            v.w = 0.f;
+            if (rem < 3) v.z = 0.f;
+            if (rem < 2) v.y = 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            a[r][i] = fmaf(v.x, w[i].x, fmaf(v.y, w[i].y, fmaf(v.z, w[i].z, fmaf(v.w, w[i].w, a[r][i]))));
+        }
+      }
+    }
+    float v[NVP];
+#pragma unroll
+    for (int i = 0; i < NVP; ++i) v[i] = i < NV ? a[i / 4][i % 4] : 0.f;
+    // each step keeps half of the values (the upper half on lanes with bit
+    // m set) plus the partner lane's same half: lane l ends with entries
+    // PER*l .. PER*l + PER - 1 summed over its SL lanes
+#pragma unroll
+    for (int h = NVP / 2, m = SL / 2; m >= 1; h >>= 1, m >>= 1) {
+      const bool up = (lane & m) != 0;
+#pragma unroll
+      for (int i = 0; i < h; ++i) {
+        const float send = up ? v[i] : v[i + h];
+        const float keep = up ? v[i + h] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+      }
+    }
+    if (valid) {
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const int idx = PER * l + i, r = idx / 4, j = idx % 4;
+        if (r < NR) out[(size_t)r * Op + og * 4 + j] = v[i];
+      }
+    }
+  }
+}
+
+// Load rows [row0, row0 + n) of a row-major [rows][K] matrix into shared
+// memory dst[o * ldw + k] (k < K); other entries are left as they are (zero).
+__device__ __forceinline__ void load_rows(const float *src, int K, int row0, int n, int ldw,
+                                          float *dst) {
+  for (int e = threadIdx.x; e < n * K; e += NT) {
+    const int o = e / K, k = e % K;
+    dst[(size_t)o * ldw + k] = src[(size_t)(row0 + o) * K + k];
+  }
+}
+
 // Load rows [row0, row0 + n) of a row-major [rows][K] matrix, transposed into
 // shared memory dst[k * ldt + o] (o < n), zero for o in [n, ncols).  Global
 // reads are coalesced along k.
@@ -279,30 +368,31 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
   // ---- every padding column and vector starts at zero
   for (size_t e = tid; e < L.total; e += NT) sm[e] = 0.f;
   __syncthreads();
-  // ---- resident weights, transposed to [k][o]; rows of outputs not owned are zero
-  load_T(p.W1, SA, i0, ni, d.Ha, d.Hap, sm + L.w1);
+  // ---- resident weights, [o][k] rows of the owned outputs (others zero)
+  load_rows(p.W1, SA, i0, ni, SAp, sm + L.w1);
   for (int o = tid; o < d.Ha; o += NT) {
     sm[L.b1 + o] = (o < ni && p.b1) ? p.b1[i0 + o] : 0.f;
     sm[L.b2 + o] = (o < ni && p.b2) ? p.b2[i0 + o] : 0.f;
   }
   for (int g = 0; g < 3; ++g) {
-    load_T(p.Wih, Hd, g * RH + j0, nj, d.Ua, d.U3p, sm + L.wih + g * d.Ua);
-    load_T(p.Whh, RH, g * RH + j0, nj, d.Ua, d.U3p, sm + L.whh + g * d.Ua);
+    load_rows(p.Wih, Hd, g * RH + j0, nj, Hdp, sm + L.wih + (size_t)g * d.Ua * Hdp);
+    load_rows(p.Whh, RH, g * RH + j0, nj, RHp, sm + L.whh + (size_t)g * d.Ua * RHp);
   }
   for (int o = tid; o < 3 * d.Ua; o += NT) {
     const int g = o / d.Ua, j = o % d.Ua;
     sm[L.bih + o] = (j < nj && p.bih) ? p.bih[g * RH + j0 + j] : 0.f;
     sm[L.bhh + o] = (j < nj && p.bhh) ? p.bhh[g * RH + j0 + j] : 0.f;
   }
-  load_T(p.W2, RH, i0, ni, d.Ha, d.Hap, sm + L.w2);
-  for (int h = 0; h < 2; ++h) load_T(p.W3, Hd, h * S + s0, ns, d.Sa, d.S2p, sm + L.w3 + h * d.Sa);
+  load_rows(p.W2, RH, i0, ni, RHp, sm + L.w2);
+  for (int h = 0; h < 2; ++h)
+    load_rows(p.W3, Hd, h * S + s0, ns, Hdp, sm + L.w3 + (size_t)h * d.Sa * Hdp);
   for (int o = tid; o < 2 * d.Sa; o += NT) {
     const int h = o / d.Sa, j = o % d.Sa;
     sm[L.b3 + o] = (j < ns && p.b3) ? p.b3[h * S + s0 + j] : 0.f;
   }
   if (actor) {
-    load_T(p.Wa1, S + RH, x0, nx, d.Hxa, d.Hxap, sm + L.wa1);
-    load_T(p.Wa2, d.Hx, a0, na, d.Axa, d.Axap, sm + L.wa2);
+    load_rows(p.Wa1, S + RH, x0, nx, d.SRp, sm + L.wa1);
+    load_rows(p.Wa2, d.Hx, a0, na, d.Hxp, sm + L.wa2);
     for (int o = tid; o < d.Hxa; o += NT) sm[L.ba1 + o] = (o < nx && p.ba1) ? p.ba1[x0 + o] : 0.f;
     for (int o = tid; o < d.Axa; o += NT) sm[L.ba2 + o] = (o < na && p.ba2) ? p.ba2[a0 + o] : 0.f;
   }
@@ -375,11 +465,6 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
   };
   bool ok = true;
 
-  const int ks1 = split_of(d.Hap, SA);
-  const int ks2a = split_of(d.U3p, Hd), ks2b = split_of(d.U3p, RH);
-  const int ks3 = split_of(d.Hap, RH);
-  const int ks4 = split_of(d.S2p, Hd);
-  const int ksx1 = actor ? split_of(d.Hxap, S + RH) : 1, ksx2 = actor ? split_of(d.Axap, d.Hx) : 1;
   float *part1 = sm + L.part1, *part2 = sm + L.part2;
 
   for (int t = 0; t < p.T; ++t) {
@@ -398,9 +483,7 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
             k < S ? sm[L.st + (size_t)r * S + k] : bel_cur[(size_t)r * RHp + (k - S)];
       }
       __syncthreads();
-      matvec_part<NR>(sm + L.wa1, d.Hxap, SR, sm + L.ain, d.SRp, ksx1, part1);
-      __syncthreads();
-      reduce_parts(part1, d.Hxap, Bc, ksx1);
+      matvec_sl<NR, 16>(sm + L.wa1, d.SRp, d.Hxap, SR, sm + L.ain, d.SRp, part1, 0, NT);
       __syncthreads();
       for (int e = tid; e < nx * Bc; e += NT) {
         const int o = e % nx, r = e / nx;
@@ -410,9 +493,7 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
       if (!(ok = wait_vec(V_HX))) break;
       // ---- actor, output: action = tanh(Wa2 x + ba2), owned entries, placed
       //      straight into every CTA's phase-1 input row
-      matvec_part<NR>(sm + L.wa2, d.Axap, d.Hx, sm + L.hx, d.Hxp, ksx2, part1);
-      __syncthreads();
-      reduce_parts(part1, d.Axap, Bc, ksx2);
+      matvec_sl<NR, 16>(sm + L.wa2, d.Hxp, d.Axap, d.Hx, sm + L.hx, d.Hxp, part1, 0, NT);
       __syncthreads();
       for (int e = tid; e < na * Bc; e += NT) {
         const int j = e % na, r = e / na;
@@ -435,9 +516,7 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
       sm[L.in1 + (size_t)r * SAp + k] = v;
     }
     __syncthreads();
-    matvec_part<NR>(sm + L.w1, d.Hap, SA, sm + L.in1, SAp, ks1, part1);
-    __syncthreads();
-    reduce_parts(part1, d.Hap, Bc, ks1);
+    matvec_sl<NR, 16>(sm + L.w1, SAp, d.Hap, SA, sm + L.in1, SAp, part1, 0, NT);
     __syncthreads();
     if (tr) p.trace[t * 16 + 10] = clock64();
     for (int e = tid; e < ni * Bc; e += NT) {
@@ -449,15 +528,9 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
     if (tr) p.trace[t * 16 + 1] = globaltimer_ns();
     // ---- phase 2: GRUCell(a, belief) for owned units
     const long long c2 = clock64();
-    matvec_part<NR>(sm + L.wih, d.U3p, Hd, sm + L.av, Hdp, ks2a, part1);
-    matvec_part<NR>(sm + L.whh, d.U3p, RH, bel_cur, RHp, ks2b, part2);
-    __syncthreads();
-    if (ks2a == ks2b) {
-      reduce_parts2(part1, part2, d.U3p, Bc, ks2a);
-    } else {
-      reduce_parts(part1, d.U3p, Bc, ks2a);
-      reduce_parts(part2, d.U3p, Bc, ks2b);
-    }
+    // (the two products side by side, each on half of the threads)
+    matvec_sl<NR, 8>(sm + L.wih, Hdp, d.U3p, Hd, sm + L.av, Hdp, part1, 0, NT / 2);
+    matvec_sl<NR, 8>(sm + L.whh, RHp, d.U3p, RH, bel_cur, RHp, part2, NT / 2, NT / 2);
     __syncthreads();
     if (tr) p.trace[t * 16 + 8] = clock64() - c2;
     for (int e = tid; e < nj * Bc; e += NT) {
@@ -480,9 +553,7 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
     if (!(ok = wait_vec(V_BEL))) break;
     if (tr) p.trace[t * 16 + 2] = globaltimer_ns();
     // ---- phase 3: q = ELU(W2 belief + b2), owned outputs
-    matvec_part<NR>(sm + L.w2, d.Hap, RH, sm + bel_nxt, RHp, ks3, part1);
-    __syncthreads();
-    reduce_parts(part1, d.Hap, Bc, ks3);
+    matvec_sl<NR, 16>(sm + L.w2, RHp, d.Hap, RH, sm + bel_nxt, RHp, part1, 0, NT);
     __syncthreads();
     for (int e = tid; e < ni * Bc; e += NT) {
       const int o = e % ni, r = e / ni;
@@ -492,9 +563,7 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
     if (!(ok = wait_vec(V_QV))) break;
     if (tr) p.trace[t * 16 + 3] = globaltimer_ns();
     // ---- phase 4: p = W3 q + b3 -> mean, std, sampled state (owned entries)
-    matvec_part<NR>(sm + L.w3, d.S2p, Hd, sm + L.qv, Hdp, ks4, part1);
-    __syncthreads();
-    reduce_parts(part1, d.S2p, Bc, ks4);
+    matvec_sl<NR, 16>(sm + L.w3, Hdp, d.S2p, Hd, sm + L.qv, Hdp, part1, 0, NT);
     __syncthreads();
     for (int e = tid; e < ns * Bc; e += NT) {
       const int j = e % ns, r = e / ns;
