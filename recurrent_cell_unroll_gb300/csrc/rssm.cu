@@ -37,7 +37,6 @@ namespace {
 constexpr int RC = 8;    // CTAs per cluster
 constexpr int NT = 512;
 constexpr int MAXBC = 8; // batch rows per cluster
-constexpr int KS_MAX = 16;
 constexpr size_t PRELOAD_MAX = 32 * 1024;  // bytes of actions+eps kept in shared memory
 constexpr size_t SMEM_CAP = 227 * 1024 - 64;  // dynamic shared memory per CTA (64 B static)
 
@@ -75,22 +74,13 @@ __host__ __device__ inline Dims make_dims(int S, int A, int Hd, int RH, int Bc, 
   return d;
 }
 
-// K split of a mat-vec with Op outputs (4 per thread) over K inputs
-__host__ __device__ inline int split_of(int Op, int K) {
-  int ks = NT / (Op / 4 > 0 ? Op / 4 : 1);
-  if (ks > KS_MAX) ks = KS_MAX;
-  const int k4 = ceil_div(K, 4);
-  if (ks > k4) ks = k4;
-  return ks < 1 ? 1 : ks;
-}
-
 // shared-memory carve-up (floats)
 struct Layout {
   size_t w1, b1, wih, whh, bih, bhh, w2, b2, w3, b3;  // weights ([o][k], both padded)
   size_t wa1, ba1, wa2, ba2;                           // actor weights (same form)
   size_t st, in1, av, bel, qv;                         // vectors, [Bc][padded width]
   size_t ain, hx;                                      // actor input [state, belief], hidden
-  size_t part1, part2;                                 // chunk partials
+  size_t part1, part2;                                 // a phase's sums
   size_t act, eps;                                     // preloaded actions / noise
   size_t total;
   bool preload;
@@ -127,12 +117,12 @@ __host__ __device__ inline Layout make_layout(const Dims &d, int T) {
   if (d.S2p > wmax) wmax = d.S2p;
   if (d.Hxap > wmax) wmax = d.Hxap;
   if (d.Axap > wmax) wmax = d.Axap;
-  L.part1 = take((size_t)KS_MAX * d.Bc * wmax);
-  // the actor's input row and hidden layer live in the phase-2 partials:
+  L.part1 = take((size_t)d.Bc * wmax);  // a phase's sums, [Bc][outputs]
+  // the actor's input row and hidden layer live in the phase-2 sums:
   // both are used between the step's last barrier and phase 2, and peers
   // write the hidden layer only after that barrier
   const size_t ain_n = (size_t)d.Bc * d.SRp, hx_n = d.Hx > 0 ? (size_t)d.Bc * d.Hxp : 0;
-  size_t p2 = (size_t)KS_MAX * d.Bc * d.U3p;
+  size_t p2 = (size_t)d.Bc * d.U3p;
   if (ain_n + hx_n > p2) p2 = ain_n + hx_n;
   L.part2 = take(p2);
   L.ain = L.part2;
@@ -151,60 +141,6 @@ __host__ __device__ inline Layout make_layout(const Dims &d, int T) {
 __device__ __forceinline__ float elu_f(float v) { return v > 0.f ? v : expm1f(v); }
 __device__ __forceinline__ float softplus_f(float v) {
   return fmaxf(v, 0.f) + log1pf(expf(-fabsf(v)));
-}
-
-// part[q][r][o] = sum over K-chunk q of Wt[k*Op + o] * V[r*ldv + k], for
-// o < Op, r < NR, q < ks.  Thread t = (4-output group, q): per 4 inputs it
-// loads a 4x4 weight block and each row's 4 inputs as 16-byte vectors
-// (broadcast across the group) and does 16*NR FMAs, so shared-memory traffic
-// stays below the FMA rate.  Op, ldv and the chunk starts are multiples of 4.
-template <int NR>
-__device__ __forceinline__ void matvec_part(const float *Wt, int Op, int K, const float *V,
-                                            int ldv, int ks, float *part) {
-  const int ng = Op / 4;
-  const int n = ng * ks;
-  const int kc = ceil_div(ceil_div(K, ks), 4) * 4;
-  for (int t = threadIdx.x; t < n; t += NT) {
-    const int og = t % ng, q = t / ng;
-    const int k0 = q * kc, k1 = min(K, k0 + kc);
-    float a[NR][4];
-#pragma unroll
-    for (int r = 0; r < NR; ++r) a[r][0] = a[r][1] = a[r][2] = a[r][3] = 0.f;
-    const float *wp = Wt + og * 4;
-    int k = k0;
-    for (; k + 3 < k1; k += 4) {
-      float4 w[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) w[i] = *reinterpret_cast<const float4 *>(wp + (size_t)(k + i) * Op);
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        const float4 v = *reinterpret_cast<const float4 *>(V + (size_t)r * ldv + k);
-        const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          a[r][0] = fmaf(vv[i], w[i].x, a[r][0]);
-          a[r][1] = fmaf(vv[i], w[i].y, a[r][1]);
-          a[r][2] = fmaf(vv[i], w[i].z, a[r][2]);
-          a[r][3] = fmaf(vv[i], w[i].w, a[r][3]);
-        }
-      }
-    }
-    for (; k < k1; ++k) {
-      const float4 w = *reinterpret_cast<const float4 *>(wp + (size_t)k * Op);
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        const float v = V[(size_t)r * ldv + k];
-        a[r][0] = fmaf(v, w.x, a[r][0]);
-        a[r][1] = fmaf(v, w.y, a[r][1]);
-        a[r][2] = fmaf(v, w.z, a[r][2]);
-        a[r][3] = fmaf(v, w.w, a[r][3]);
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < NR; ++r)
-      *reinterpret_cast<float4 *>(part + ((size_t)q * NR + r) * Op + og * 4) =
-          make_float4(a[r][0], a[r][1], a[r][2], a[r][3]);
-  }
 }
 
 // out[r*Op + o] = sum over k < K of Wo[o*ldw + k] * V[r*ldv + k], for o < Op
@@ -294,17 +230,6 @@ __device__ __forceinline__ void load_rows(const float *src, int K, int row0, int
   }
 }
 
-// Load rows [row0, row0 + n) of a row-major [rows][K] matrix, transposed into
-// shared memory dst[k * ldt + o] (o < n), zero for o in [n, ncols).  Global
-// reads are coalesced along k.
-__device__ __forceinline__ void load_T(const float *src, int K, int row0, int n, int ncols,
-                                       int ldt, float *dst) {
-  for (int e = threadIdx.x; e < ncols * K; e += NT) {
-    const int o = e / K, k = e % K;
-    dst[(size_t)k * ldt + o] = o < n ? src[(size_t)(row0 + o) * K + k] : 0.f;
-  }
-}
-
 // 4-byte asynchronous store into cluster CTA shared memory (address from
 // mapa), completing as 4 bytes of complete_tx on that CTA's mbarrier
 __device__ __forceinline__ void st_async_b32(uint32_t addr, float v, uint32_t bar) {
@@ -316,28 +241,6 @@ __device__ __forceinline__ void st_async_b32(uint32_t addr, float v, uint32_t ba
 // the broadcast vectors, one mbarrier each
 enum Vec { V_ST = 0, V_HX, V_ACT, V_AV, V_BEL, V_QV, NVEC };
 
-// part[0][r][o] = sum over q of part[q][r][o], spread over all threads (the
-// consumers then read one value per output instead of ks).  Callers
-// synchronise before and after.
-__device__ __forceinline__ void reduce_parts(float *part, int Op, int nr, int ks) {
-  const int n = nr * Op;
-  for (int e = threadIdx.x; e < n; e += NT) {
-    float a = part[e];
-    for (int q = 1; q < ks; ++q) a += part[(size_t)q * n + e];
-    part[e] = a;
-  }
-}
-// The same for two partial arrays of equal shape in one pass.
-__device__ __forceinline__ void reduce_parts2(float *pa, float *pb, int Op, int nr, int ks) {
-  const int n = nr * Op;
-  for (int e = threadIdx.x; e < 2 * n; e += NT) {
-    float *part = e < n ? pa : pb;
-    const int i = e < n ? e : e - n;
-    float a = part[i];
-    for (int q = 1; q < ks; ++q) a += part[(size_t)q * n + i];
-    part[i] = a;
-  }
-}
 __device__ __forceinline__ float part_sum(const float *part, int Op, int r, int o) {
   return part[(size_t)r * Op + o];
 }
@@ -640,7 +543,7 @@ __host__ __device__ inline BwdDims make_bdims(int S, int Hd, int RH, int Bc) {
   return d;
 }
 struct BwdLayout {
-  size_t w3, w2, whh, wih, w1s;       // weights, [k][o]
+  size_t w3, w2, whh, wih, w1s;       // weights, [o][k] (columns of W as rows)
   size_t dp, dv, dra, du, cs, gh, dhz;  // vectors, [Bc][padded width]
   size_t part1, part2, total;
 };
@@ -648,11 +551,11 @@ __host__ __device__ inline BwdLayout make_blayout(const BwdDims &d) {
   BwdLayout L;
   size_t o = 0;
   auto take = [&](size_t n) { size_t r = o; o += (n + 3) & ~size_t(3); return r; };
-  L.w3 = take((size_t)2 * d.S * d.Hap);    // W3^T dp -> owned outputs of Hd
-  L.w2 = take((size_t)d.Hd * d.Uap);       // W2^T dv -> owned units
-  L.whh = take((size_t)3 * d.RH * d.Uap);  // W_hh^T dR -> owned units
-  L.wih = take((size_t)3 * d.RH * d.Hap);  // W_ih^T dA -> owned outputs of Hd
-  L.w1s = take((size_t)d.Hd * d.Sp);       // W1[:, :S]^T du -> every state entry
+  L.w3 = take((size_t)d.Hap * d.S2p);   // W3^T dp -> owned outputs of Hd
+  L.w2 = take((size_t)d.Uap * d.Hdp);   // W2^T dv -> owned units
+  L.whh = take((size_t)d.Uap * d.G3p);  // W_hh^T dR -> owned units
+  L.wih = take((size_t)d.Hap * d.G3p);  // W_ih^T dA -> owned outputs of Hd
+  L.w1s = take((size_t)d.Sp * d.Hdp);   // W1[:, :S]^T du -> every state entry
   L.dp = take((size_t)d.Bc * d.S2p);
   L.dv = take((size_t)d.Bc * d.Hdp);
   L.dra = take((size_t)d.Bc * 2 * d.G3p);  // per row: dR [3RH], then dA [3RH]
@@ -662,19 +565,20 @@ __host__ __device__ inline BwdLayout make_blayout(const BwdDims &d) {
   L.dhz = take((size_t)d.Bc * d.Uap);
   int wmax = d.Hap > d.Uap ? d.Hap : d.Uap;
   if (d.Sp > wmax) wmax = d.Sp;
-  L.part1 = take((size_t)KS_MAX * d.Bc * wmax);
-  L.part2 = take((size_t)KS_MAX * d.Bc * wmax);
+  L.part1 = take((size_t)d.Bc * wmax);  // a phase's sums, [Bc][outputs]
+  L.part2 = take((size_t)d.Bc * wmax);
   L.total = o;
   return L;
 }
 
-// dst[k * ldt + o] = src[k * ld + col0 + o] for k < K, o < n; zero for o in
-// [n, ncols) (a column slice of a row-major matrix, kept [k][o])
+// dst[o * ldw + k] = src[k * ld + col0 + o] for k < K, o < n (a column
+// slice of a row-major matrix, kept as rows [o][k]; other entries are left
+// as they are, zero)
 __device__ __forceinline__ void load_cols(const float *src, int ld, int K, int col0, int n,
-                                          int ncols, int ldt, float *dst) {
-  for (int e = threadIdx.x; e < ncols * K; e += NT) {
-    const int k = e / ncols, o = e % ncols;
-    dst[(size_t)k * ldt + o] = o < n ? src[(size_t)k * ld + col0 + o] : 0.f;
+                                          int ldw, float *dst) {
+  for (int e = threadIdx.x; e < n * K; e += NT) {
+    const int k = e / n, o = e % n;
+    dst[(size_t)o * ldw + k] = src[(size_t)k * ld + col0 + o];
   }
 }
 
@@ -698,11 +602,11 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
 
   for (size_t e = tid; e < L.total; e += NT) sm[e] = 0.f;
   __syncthreads();
-  load_cols(p.W3, Hd, S2, i0, ni, d.Ha, d.Hap, sm + L.w3);
-  load_cols(p.W2, RH, Hd, j0, nj, d.Ua, d.Uap, sm + L.w2);
-  load_cols(p.Whh, RH, G, j0, nj, d.Ua, d.Uap, sm + L.whh);
-  load_cols(p.Wih, Hd, G, i0, ni, d.Ha, d.Hap, sm + L.wih);
-  load_cols(p.W1, S + p.A, Hd, 0, S, S, d.Sp, sm + L.w1s);
+  load_cols(p.W3, Hd, S2, i0, ni, d.S2p, sm + L.w3);
+  load_cols(p.W2, RH, Hd, j0, nj, d.Hdp, sm + L.w2);
+  load_cols(p.Whh, RH, G, j0, nj, d.G3p, sm + L.whh);
+  load_cols(p.Wih, Hd, G, i0, ni, d.G3p, sm + L.wih);
+  load_cols(p.W1, S + p.A, Hd, 0, S, d.Hdp, sm + L.w1s);
   __shared__ uint64_t vbar[NBVEC];
   __shared__ int s_ok;
   if (tid == 0) {
@@ -741,8 +645,6 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
     __syncthreads();
     return s_ok != 0;
   };
-  const int ks_a = split_of(d.Hap, S2), ks_b = split_of(d.Uap, Hd);
-  const int ks_c = split_of(d.Uap, G), ks_d = split_of(d.Hap, G), ks_e = split_of(d.Sp, Hd);
   float *part1 = sm + L.part1, *part2 = sm + L.part2;
   bool ok = true;
 
@@ -768,9 +670,7 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
       sm[L.dp + (size_t)r * d.S2p + S + j] = dsd;
     }
     __syncthreads();
-    matvec_part<NR>(sm + L.w3, d.Hap, S2, sm + L.dp, d.S2p, ks_a, part1);
-    __syncthreads();
-    reduce_parts(part1, d.Hap, Bc, ks_a);
+    matvec_sl<NR, 16>(sm + L.w3, d.S2p, d.Hap, S2, sm + L.dp, d.S2p, part1, 0, NT);
     __syncthreads();
     for (int e = tid; e < ni * Bc; e += NT) {
       const int o = e % ni, r = e / ni;
@@ -784,9 +684,7 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
     }
     if (!(ok = wait_vec(BV_DV))) break;
     // ---- phase 2: dh of the owned units, their gate gradients; dR and dA broadcast
-    matvec_part<NR>(sm + L.w2, d.Uap, Hd, sm + L.dv, d.Hdp, ks_b, part1);
-    __syncthreads();
-    reduce_parts(part1, d.Uap, Bc, ks_b);
+    matvec_sl<NR, 16>(sm + L.w2, d.Hdp, d.Uap, Hd, sm + L.dv, d.Hdp, part1, 0, NT);
     __syncthreads();
     for (int e = tid; e < nj * Bc; e += NT) {
       const int jj = e % nj, r = e / nj, j = j0 + jj;
@@ -820,11 +718,10 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
     if (!(ok = wait_vec(BV_DRA))) break;
     // ---- phase 3: W_hh^T dR for the owned units (carried to step t-1),
     //      du = (W_ih^T dA) * ELU'(u) for the owned outputs, broadcast
-    matvec_part<NR>(sm + L.whh, d.Uap, G, sm + L.dra, ldra, ks_c, part1);
-    matvec_part<NR>(sm + L.wih, d.Hap, G, sm + L.dra + d.G3p, ldra, ks_d, part2);
-    __syncthreads();
-    reduce_parts(part1, d.Uap, Bc, ks_c);
-    reduce_parts(part2, d.Hap, Bc, ks_d);
+    // (the two products side by side, each on half of the threads)
+    matvec_sl<NR, 16>(sm + L.whh, d.G3p, d.Uap, G, sm + L.dra, ldra, part1, 0, NT / 2);
+    matvec_sl<NR, 16>(sm + L.wih, d.G3p, d.Hap, G, sm + L.dra + d.G3p, ldra, part2, NT / 2,
+                      NT / 2);
     __syncthreads();
     for (int e = tid; e < nj * Bc; e += NT) {
       const int jj = e % nj, r = e / nj;
@@ -842,9 +739,7 @@ __global__ void __cluster_dims__(RC, 1, 1) __launch_bounds__(NT, 1)
     }
     if (!(ok = wait_vec(BV_DU))) break;
     // ---- phase 4: ds_{t-1} = W1[:, :S]^T du (every CTA, every state entry)
-    matvec_part<NR>(sm + L.w1s, d.Sp, Hd, sm + L.du, d.Hdp, ks_e, part1);
-    __syncthreads();
-    reduce_parts(part1, d.Sp, Bc, ks_e);
+    matvec_sl<NR, 16>(sm + L.w1s, d.Hdp, d.Sp, Hd, sm + L.du, d.Hdp, part1, 0, NT);
     __syncthreads();
     for (int e = tid; e < Bc * S; e += NT) {
       const int r = e / S, k = e % S;
