@@ -230,6 +230,72 @@ __device__ __forceinline__ void chunk_matmul_rm8(const WT *Wsm, int Rx, int Kx, 
   }
 }
 
+// The same product with W_hh kept [Rx][Kx] (gate row r's K columns
+// contiguous) and K split over the 16 lanes of a half-warp (lane l: columns
+// 4l, 4l + 64, ...: consecutive 16-byte words of one row across the lanes).
+// Half-warp g takes a tile of 8 batch rows x TC = Rx / 4 gate rows (the rows
+// in CB / 8 row tiles, the gate rows in 4 column tiles), reduce-scatters its
+// tile over the 16 lanes by shuffles, and after a CTA barrier (hs is dead)
+// writes the whole sums over the h rows: red[i * Rx + r] (one K slice).
+// Every thread of the CTA calls it.
+template <int TC>
+__device__ __forceinline__ void chunk_matmul_sl(const float *Wr, int Rx, int Kx, const float *hs,
+                                                int HS, int CB, float *red) {
+  constexpr int TR = 8, SL = 16, NV = TR * TC;
+  constexpr int PER0 = (NV + SL - 1) / SL;
+  constexpr int PER = PER0 <= 1 ? 1 : (PER0 <= 2 ? 2 : (PER0 <= 4 ? 4 : 8));  // sums per lane
+  constexpr int NVP = SL * PER;
+  const int tid = threadIdx.x, g = tid / SL, l = tid % SL, lane = tid & 31;
+  const bool act = g < (CB / TR) * 4;  // (warp-uniform: an even number of tiles)
+  const int tr = g / 4, tcol = g % 4;
+  float acc[TR][TC];
+#pragma unroll
+  for (int r = 0; r < TR; ++r)
+#pragma unroll
+    for (int c = 0; c < TC; ++c) acc[r][c] = 0.f;
+  if (act) {
+    const float *hp = hs + (size_t)tr * TR * HS;
+    const float *wp = Wr + (size_t)tcol * TC * Kx;
+    for (int k = 4 * l; k < Kx; k += 4 * SL) {
+      float4 w[TC];
+#pragma unroll
+      for (int c = 0; c < TC; ++c) w[c] = *reinterpret_cast<const float4 *>(wp + (size_t)c * Kx + k);
+#pragma unroll
+      for (int r = 0; r < TR; ++r) {
+        const float4 h = *reinterpret_cast<const float4 *>(hp + (size_t)r * HS + k);
+#pragma unroll
+        for (int c = 0; c < TC; ++c)
+          acc[r][c] = fmaf(h.x, w[c].x, fmaf(h.y, w[c].y, fmaf(h.z, w[c].z, fmaf(h.w, w[c].w, acc[r][c]))));
+      }
+    }
+  }
+  float v[NVP];
+#pragma unroll
+  for (int i = 0; i < NVP; ++i) v[i] = i < NV ? acc[i / TC][i % TC] : 0.f;
+  // each step keeps half of the values (the upper half on lanes with bit m
+  // set) plus the partner lane's same half: lane l ends with entries
+  // PER*l .. PER*l + PER - 1 summed over its 16 lanes
+#pragma unroll
+  for (int h = NVP / 2, m = SL / 2; m >= 1; h >>= 1, m >>= 1) {
+    const bool up = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float send = up ? v[i] : v[i + h];
+      const float keep = up ? v[i + h] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+  }
+  __syncthreads();  // hs is dead: red takes its place
+  if (act) {
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int idx = PER * l + i;
+      if (idx < NV)
+        red[(size_t)(tr * TR + idx / TC) * Rx + tcol * TC + idx % TC] = v[i];
+    }
+  }
+}
+
 // hs[k][i] = src[(row0 + i) * ld + k] for i < nr (0 for i >= nr), k < Kx.
 // Loads are issued LB at a time into registers before any store, so their L2
 // latencies overlap.
@@ -271,9 +337,15 @@ struct Smem {
 __host__ __device__ inline bool rowmajor_h(const RecParams &p, size_t wsz) {
   return wsz == 4 && p.proj == 0;
 }
-// ... and multiplied in 8 x 4 tiles whose partial sums reuse the h buffer
+// ... multiplied with K split over half-warps and summed by shuffles (W_hh
+// kept [Rp][Kp]), the sums written over the h buffer
+__host__ __device__ inline bool rowmajor_hsl(const RecParams &p, size_t wsz) {
+  return rowmajor_h(p, wsz) && p.CB % 8 == 0 && p.Rp % 4 == 0 && p.Rp >= 4 && p.Rp <= 32 &&
+         (p.CB / 8) * 4 * 16 <= NT && p.Rp <= p.Kp + 4;
+}
+// ... else in 8 x 4 tiles whose partial sums reuse the h buffer
 __host__ __device__ inline bool rowmajor_h8(const RecParams &p, size_t wsz) {
-  return rowmajor_h(p, wsz) && make_split8(p.CB, p.Rp, p.Kp).tiles > 0;
+  return rowmajor_h(p, wsz) && !rowmajor_hsl(p, wsz) && make_split8(p.CB, p.Rp, p.Kp).tiles > 0;
 }
 __host__ __device__ inline Smem smem_layout(const RecParams &p, size_t wsz) {
   const bool proj = p.proj > 0;
@@ -293,8 +365,8 @@ __host__ __device__ inline Smem smem_layout(const RecParams &p, size_t wsz) {
   L.red = o;
   const Split s1 = make_split(p.CB, p.Rp, p.Kp);
   size_t red = (size_t)s1.ks * p.CB * p.Rp;
-  if (rowmajor_h8(p, wsz)) {
-    L.red = L.hs;  // (the partial sums overwrite the h rows)
+  if (rowmajor_h8(p, wsz) || rowmajor_hsl(p, wsz)) {
+    L.red = L.hs;  // (the sums overwrite the h rows)
     red = 0;
   }
   if (proj) {
@@ -345,7 +417,13 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
 
   {  // resident weights
     const WT *gW = reinterpret_cast<const WT *>(p.Whh[d]) + (size_t)ug * Kp * p.Rp;
-    for (int i = threadIdx.x; i < Kp * p.Rp; i += NT) Ws[i] = gW[i];
+    if (rowmajor_hsl(p, sizeof(WT))) {
+      // [Kp][Rp] -> [Rp][Kp]
+      for (int i = threadIdx.x; i < Kp * p.Rp; i += NT)
+        Ws[(size_t)(i % p.Rp) * Kp + i / p.Rp] = gW[i];
+    } else {
+      for (int i = threadIdx.x; i < Kp * p.Rp; i += NT) Ws[i] = gW[i];
+    }
     if (prow) {
       const WT *gR = reinterpret_cast<const WT *>(p.Whr[d]) + (size_t)ug * Hp * p.Pcp;
       for (int i = threadIdx.x; i < Hp * p.Pcp; i += NT) Wr[i] = gR[i];
@@ -439,8 +517,9 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
   const bool drop = p.drop_arrival && blockIdx.x == 0;
   if (!group_barrier(ctr, ++nbar * p.NU, p.err, p.timeout_ns, drop)) return;
 
-  const bool rm8 = rowmajor_h8(p, sizeof(WT));
-  const Split sp1 = rm8 ? make_split8(CB, p.Rp, Kp) : make_split(CB, p.Rp, Kp);
+  const bool rm8 = rowmajor_h8(p, sizeof(WT)), rmsl = rowmajor_hsl(p, sizeof(WT));
+  const Split sp1 = rmsl ? Split{(CB / 8) * 4, 1, Kp}
+                         : (rm8 ? make_split8(CB, p.Rp, Kp) : make_split(CB, p.Rp, Kp));
   const Split sp2 = proj ? make_split(CB, p.Pcp, Hp) : Split{0, 0, 0};
 
   for (int step = 0; step < p.T; ++step) {
@@ -484,10 +563,23 @@ __global__ void __launch_bounds__(NT, 1) rec_simt_kernel(const RecParams p) {
           return;
         }
         if (tr && cb == 0) p.trace[step * 16 + 3] = globaltimer_ns();
-        if (rm8)
+        if (rmsl) {
+          const float *Wf = reinterpret_cast<const float *>(Ws);
+          switch (p.Rp / 4) {
+            case 1: chunk_matmul_sl<1>(Wf, p.Rp, Kp, hs, Kp + 4, CB, red); break;
+            case 2: chunk_matmul_sl<2>(Wf, p.Rp, Kp, hs, Kp + 4, CB, red); break;
+            case 3: chunk_matmul_sl<3>(Wf, p.Rp, Kp, hs, Kp + 4, CB, red); break;
+            case 4: chunk_matmul_sl<4>(Wf, p.Rp, Kp, hs, Kp + 4, CB, red); break;
+            case 5: chunk_matmul_sl<5>(Wf, p.Rp, Kp, hs, Kp + 4, CB, red); break;
+            case 6: chunk_matmul_sl<6>(Wf, p.Rp, Kp, hs, Kp + 4, CB, red); break;
+            case 7: chunk_matmul_sl<7>(Wf, p.Rp, Kp, hs, Kp + 4, CB, red); break;
+            default: chunk_matmul_sl<8>(Wf, p.Rp, Kp, hs, Kp + 4, CB, red); break;
+          }
+        } else if (rm8) {
           chunk_matmul_rm8(Ws, p.Rp, Kp, hs, Kp + 4, CB, red, sp1);
-        else
+        } else {
           chunk_matmul_rm(Ws, p.Rp, Kp, hs, Kp + 4, CB, red, sp1);
+        }
       } else {
         load_chunk_T(hcur, Kp, cb, nr, Kp, CB, hs);
         __syncthreads();
