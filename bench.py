@@ -442,7 +442,6 @@ def make_train_runner(spec, inp, dev, net, d):
 TRAFFIC = {
     ("gru_bf16_3L_T512_B256_1024", "recurrent_tc"): 1961.3e6,
     ("lstmp_bf16_2L_T1000_B32_80x1024p256", "recurrent_tc_lstmp"): 43.7e6,
-    ("bilstm_f32_varlen_B64_T500_256x512", "recurrent_simt"): 358.0e6,
     ("lstm_f32_T80_B1_512x256", "recurrent_cluster"): 1.41e6,
     ("lstm_train_f32_T500_B64_256x512", "bwd_recurrent"): 634.4e6,
     ("bilstm_train_f32_varlen_B64_T500_256x512", "bwd_recurrent"): 455.9e6,
