@@ -442,9 +442,13 @@ def make_train_runner(spec, inp, dev, net, d):
 TRAFFIC = {
     ("gru_bf16_3L_T512_B256_1024", "recurrent_tc"): 1961.3e6,
     ("lstmp_bf16_2L_T1000_B32_80x1024p256", "recurrent_tc_lstmp"): 43.7e6,
+    ("bilstm_f32_varlen_B64_T500_256x512", "recurrent_simt"): 358.1e6,
     ("lstm_f32_T80_B1_512x256", "recurrent_cluster"): 1.41e6,
+    ("rssm_f32_B50_T50_S20_A6_H200", "rssm_unroll"): 1.55e6,
+    ("rssm_actor_f32_B50_T50_S20_A6_H200_X200", "rssm_unroll"): 1.69e6,
     ("lstm_train_f32_T500_B64_256x512", "bwd_recurrent"): 634.4e6,
     ("bilstm_train_f32_varlen_B64_T500_256x512", "bwd_recurrent"): 455.9e6,
+    ("rssm_train_f32_B50_T50_S20_A6_H200", "rssm_bwd_chain"): 18.7e6,
     ("gru_train_bf16_3L_T512_B256_1024", "bwd_recurrent_tc"): 6688.3e6,
 }
 
