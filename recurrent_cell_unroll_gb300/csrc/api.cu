@@ -1189,6 +1189,9 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
   // transposed per-step streams ([rows][ldm8], column t*B + b)
   const int ldm8 = round_up(M, 8);
   const bool gru16 = h->dtype == RCU_BF16 && cell == RCU_GRU;
+  // the tcgen05 GRU reverse-time kernel can run (its transposed inputs)
+  const bool tcb_any = gru16 && P == 0 && !lengths && h->force_path != 1 &&
+                       tc_bwd_supported(H, B, h->nsm);
   const int ldh = round_up(H, 8), ldo = round_up(Ho, 8);
   int kmax = std::max(H, DHo);
   for (int l = 0; l < L; ++l) kmax = std::max(kmax, h->in_l[l]);
@@ -1200,7 +1203,9 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
                // [M][G], or transposed [G][ldm8] for the tcgen05 GRU kernel
                o_zin = take((size_t)G * ldm8), o_zh = take((size_t)G * ldm8),
                // that kernel's h_{t-1}^T and dy^T
-               o_hpt = take(gru16 ? (size_t)Ho * ldm8 : 0), o_dyt = take(gru16 ? (size_t)Ho * ldm8 : 0), o_cs = take(cell == RCU_LSTM ? TBH : 0), o_da = take(TBG),
+               o_hpt = take(tcb_any ? (size_t)Ho * ldm8 : 0),
+               o_dyt = take(tcb_any ? (size_t)Ho * ldm8 : 0),
+               o_cs = take(cell == RCU_LSTM ? TBH : 0), o_da = take(TBG),
                o_dr = take(cell == RCU_GRU ? TBG : 0), o_dya = take(TBY), o_dyb = take(TBY),
                o_t1 = take(TBG), o_t2 = take(TBK), o_t3 = take(cell == RCU_GRU ? TBG : 0),
                o_t4 = take(TBO), o_wt = take((size_t)kmax * G),
