@@ -7,11 +7,12 @@
 // The sequential part is only the recurrence of the hidden-state gradient,
 //     dh_{t-1} = W_hh^T dR_t (+ z_t * dh_t for the GRU),
 // which bwd_rec_kernel runs as one persistent cooperative launch over all
-// steps in reverse time: each CTA owns U hidden units (all batch rows) with
-// their columns of W_hh resident in shared memory, computes the gate
-// gradients of its units from the saved activations, publishes them, crosses
-// one bounded grid barrier, and forms its units' dh_{t-1} from everyone's
-// gate gradients.  Everything else is parallel over steps: the pre-activations
+// steps in reverse time: each CTA owns U hidden units of a batch group with
+// W_hh columns resident in shared memory (its own units', or with K split
+// over a CTA pair, the pair's units over half of K: bwd_rec_pair_kernel),
+// computes the gate gradients of its units from the saved activations,
+// publishes them, crosses one bounded barrier per batch group, and forms its
+// units' dh_{t-1} from everyone's gate gradients.  Everything else is parallel over steps: the pre-activations
 // are recomputed as two GEMMs (X W_ih^T, H_prev W_hh^T) once every layer's
 // output sequence is known, the LSTM cell sequence is one elementwise scan
 // (bwd_prep_kernel), and the weight and input gradients are GEMMs over all

@@ -14,7 +14,10 @@
 //               them through a swizzled 4 KB shared buffer per warp, add the
 //               bias and write fully coalesced 128-byte rows.
 // Two accumulators (2 x 256 columns) let the epilogue of tile i overlap the
-// MMAs of tile i+1.  Every mbarrier wait is bounded.
+// MMAs of tile i+1.  Every mbarrier wait is bounded.  Tiles are rastered so
+// the operand with fewer tiles varies fastest.  The same kernel runs batched
+// products (3-D tensor maps) and split-K partials (K cut into chunks, each
+// chunk's product to its own output plane, summed afterwards in order).
 #include <cudaTypedefs.h>
 
 #include <algorithm>
