@@ -9,8 +9,10 @@
 //      exchange buffer in L2,
 //   2. computes its slice of h_{t-1} W_hh^T (the "recurrent hidden-hidden
 //      dense" of "[TOPI] TE implementation of LSTM using scan",
-//      apache/tvm PR 11531) with fp32 FFMA: 4x4 register tiles, K split over
-//      at most 8 thread groups,
+//      apache/tvm PR 11531) with fp32 FFMA: for fp32 exchange rows, K split
+//      over the 16 lanes of a half-warp and summed by shuffles (8 x 8 or
+//      fewer register tiles), else 8x4 or 4x4 register tiles with K split
+//      over at most 8 thread groups,
 //   3. adds the input projection G (loaded for the step before the previous
 //      step's barrier, so its HBM latency is off the critical path), applies
 //      the gate nonlinearities and the cell update, and writes h_t (exchange

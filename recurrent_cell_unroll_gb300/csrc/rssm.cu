@@ -9,10 +9,10 @@
 // which the Python loop on the page runs as ~10 launches per step.  Here one
 // launch runs all T steps.  A thread-block cluster of RC CTAs holds one copy
 // of every weight, each CTA the rows of the outputs it owns, resident in
-// shared memory (transposed, [k][o]).  Each phase is a batched mat-vec over
-// the cluster's batch rows spread across all threads of the CTA as
-// (output, row, K-chunk); the chunk partials are summed from shared memory,
-// and the CTA's output slice is broadcast into every CTA's shared memory with
+// shared memory ([o][k]).  Each phase is a batched mat-vec over the
+// cluster's batch rows: a group of 8 or 16 lanes per 4 outputs splits K and
+// sums its partials by shuffles, and the CTA's output slice is broadcast into
+// every CTA's shared memory with
 // asynchronous distributed-shared-memory stores (st.async), each counting its
 // bytes on the receiving CTA's mbarrier for that vector.  A CTA starts the
 // next phase as soon as all bytes of the vector it needs have landed: no
