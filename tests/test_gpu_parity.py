@@ -81,6 +81,9 @@ SMALL = [
     wl.GRU_3L.scaled(dtype="f32", layers=2, bidir=True, T=9, B=5, in_dim=16, hidden=24,
                      varlen=(1, 9)),
     wl.GRU_3L.scaled(layers=1, T=5, B=1, in_dim=8, hidden=1024),
+    # fp32 SIMT kernel with 36 gate rows per CTA (9 units): beyond the
+    # half-warp tiles' 32, so the 8 x 4 register tiles
+    wl.LSTM_T80.scaled(name="lstm_wide", T=4, B=8, in_dim=32, hidden=1280),
     # tensor-core recurrent kernel: two batch groups with a ragged tail, ragged units
     wl.LSTM_T80.scaled(name="lstm_bf16", dtype="bf16", layers=2, T=12, B=150, in_dim=40,
                        hidden=70, h0_std=0.5, c0_std=0.5),
