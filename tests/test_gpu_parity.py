@@ -550,6 +550,9 @@ def test_two_handles_two_threads():
     wl.RSSM_B50.scaled(T=7, B=3, state_dim=5, action_dim=0, hidden=33, rnn_hidden=17,
                        state0_std=1.0, belief0_std=0.5),
     wl.RSSM_B50.scaled(T=4, B=70, state_dim=30, action_dim=3, hidden=64, rnn_hidden=96),
+    # 8 batch rows per cluster (the most): each lane of the shuffle-reduced
+    # mat-vecs ends with several sums
+    wl.RSSM_B50.scaled(T=5, B=130, state_dim=20, action_dim=6, hidden=100, rnn_hidden=60),
 ], ids=lambda s: f"T{s.T}-B{s.B}-S{s.state_dim}-H{s.hidden}-RH{s.rnn_hidden}")
 def test_rssm_parity(spec):
     inp = wl.make_rssm_inputs(spec, seed=21)
