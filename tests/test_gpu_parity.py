@@ -576,6 +576,8 @@ def test_rssm_parity(spec):
     (wl.RSSM_B50.scaled(T=9, B=70, state_dim=13, action_dim=5, hidden=72, rnn_hidden=40,
                         state0_std=1.0, belief0_std=0.5), 37),
     (wl.RSSM_B50.scaled(T=3, B=1, state_dim=4, action_dim=11, hidden=16, rnn_hidden=9), 3),
+    # eight batch rows per cluster through the actor phases too
+    (wl.RSSM_B50.scaled(T=4, B=130, state_dim=12, action_dim=4, hidden=48, rnn_hidden=40), 24),
 ], ids=lambda v: getattr(v, "name", f"hx{v}"))
 def test_rssm_actor_parity(spec, hx):
     """Unroll variant 2: the actions come from the actor on the device and
