@@ -222,6 +222,7 @@ __device__ __forceinline__ void bwd_rec_body(const BwdParams &p) {
       if (j >= nu) continue;
       const int u = u0 + j, b = b0 + bl;
       const size_t r = (size_t)t * B + b;
+      if (!RCU_DCHECK(b < B && u < H && r < (size_t)p.T * B, p.err)) continue;
       float *da = p.DA + r * G;
       if (p.lengths && t >= clamp_len(p.lengths[b], p.T)) {
         // a step past the row's end: no gate gradient, and the carried dh
@@ -302,6 +303,7 @@ __device__ __forceinline__ void bwd_rec_body(const BwdParams &p) {
         const int b = e / kc4, q = e % kc4, k = k0 + 4 * q;
         const float *src = drt + (size_t)(b0 + b) * G + k;
         float *dst = xb + (size_t)b * KCP + 4 * q;
+        if (!RCU_DCHECK(b0 + b < B && kbase + k + 4 <= Gp, p.err)) continue;
         if (vec) {
           cp_async16(dst, src);
         } else {
@@ -436,7 +438,7 @@ __device__ __forceinline__ void bwd_rec_body(const BwdParams &p) {
   }
   for (int e = tid; ok && e < Bl * U; e += NT) {
     const int b = e / U, j = e % U;
-    if (j >= nu) continue;
+    if (j >= nu || !RCU_DCHECK(b0 + b < B && u0 + j < H, p.err)) continue;
     if (p.dh0) p.dh0[(size_t)(b0 + b) * H + u0 + j] = dhrec[e];
     if (lstm && p.dc0) p.dc0[(size_t)(b0 + b) * H + u0 + j] = dcs[e];
   }

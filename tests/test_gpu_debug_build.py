@@ -61,6 +61,22 @@ for got, want in ((dx, ref["dx"]), (dh0, ref["dh0"])):
     e = float(np.abs(got.cpu().numpy() - want).max() / np.abs(want).max())
     assert e <= 2e-2, ("backward", e)
 net.close()
+# the FFMA reverse-time kernel with its K split over a CTA pair (fp32 LSTM)
+spec = wl.LSTM_T80.scaled(T=7, B=9, in_dim=12, hidden=40, layers=2, h0_std=0.5, c0_std=0.5)
+inp = wl.make_rnn_inputs(spec, seed=35)
+dy = torch.randn((spec.T, spec.B, spec.hidden), generator=torch.Generator().manual_seed(35))
+net = binding.RNN.from_spec(spec)
+net.set_weights(inp["weights"])
+dx, dh0, dc0, _ = net.backward(inp["x"].to(dev), dy.to(dev), h0=inp["h0"].to(dev),
+                               c0=inp["c0"].to(dev))
+st = net.status()
+assert st == 0, (spec.name, st, binding.load().rcu_last_error())
+ref = oracle.rnn_backward(oracle.LSTM, inp["x"], inp["weights"], dy, hidden=spec.hidden,
+                          h0=inp["h0"], c0=inp["c0"])
+for got, want in ((dx, ref["dx"]), (dh0, ref["dh0"]), (dc0, ref["dc0"])):
+    e = float(np.abs(got.cpu().numpy() - want).max() / np.abs(want).max())
+    assert e <= 1e-4, ("fp32 backward", e)
+net.close()
 print("debug build ok")
 """
 
