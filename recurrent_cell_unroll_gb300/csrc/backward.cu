@@ -139,6 +139,10 @@ struct BwdParams {
   unsigned long long *trace;  // NULL, or stamps of CTA 0 (row = reverse step)
 };
 
+__device__ __forceinline__ void prefetch_l2(const float *q) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(q));
+}
+
 __device__ __forceinline__ void rstamp(const BwdParams &p, int s, int slot) {
   if (p.trace && blockIdx.x == 0 && threadIdx.x == 0)
     p.trace[(size_t)s * 16 + slot] = globaltimer_ns();
@@ -223,6 +227,22 @@ __device__ __forceinline__ void bwd_rec_body(const BwdParams &p) {
       const int u = u0 + j, b = b0 + bl;
       const size_t r = (size_t)t * B + b;
       if (!RCU_DCHECK(b < B && u < H && r < (size_t)p.T * B, p.err)) continue;
+      if (t > 0) {
+        // the next step's (t - 1) inputs of this (row, unit) into L2 while
+        // the barrier and the mat-vec run: its gate phase then waits for L2,
+        // not HBM
+        const size_t rn = r - B;
+        prefetch_l2(p.dy + rn * H + u);
+        for (int q = 0; q < (lstm ? 4 : 3); ++q) prefetch_l2(p.gates + rn * G + q * H + u);
+        if (lstm) {
+          prefetch_l2(p.cs + rn * H + u);
+          if (t > 1) prefetch_l2(p.cs + (rn - B) * H + u);
+          if (p.cr) prefetch_l2(p.cr + rn * H + u);
+        } else {
+          prefetch_l2(p.zh + rn * G + 2 * H + u);
+          prefetch_l2(p.hp + rn * H + u);
+        }
+      }
       float *da = p.DA + r * G;
       if (p.lengths && t >= clamp_len(p.lengths[b], p.T)) {
         // a step past the row's end: no gate gradient, and the carried dh
