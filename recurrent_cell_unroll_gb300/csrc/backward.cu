@@ -227,10 +227,10 @@ __device__ __forceinline__ void bwd_rec_body(const BwdParams &p) {
       const int u = u0 + j, b = b0 + bl;
       const size_t r = (size_t)t * B + b;
       if (!RCU_DCHECK(b < B && u < H && r < (size_t)p.T * B, p.err)) continue;
-      if (t > 0) {
+      if (t > 0 && !(p.lengths && t - 1 >= clamp_len(p.lengths[b], p.T))) {
         // the next step's (t - 1) inputs of this (row, unit) into L2 while
         // the barrier and the mat-vec run: its gate phase then waits for L2,
-        // not HBM
+        // not HBM (rows past their end at t - 1 read nothing there)
         const size_t rn = r - B;
         prefetch_l2(p.dy + rn * H + u);
         for (int q = 0; q < (lstm ? 4 : 3); ++q) prefetch_l2(p.gates + rn * G + q * H + u);
