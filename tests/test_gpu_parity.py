@@ -327,6 +327,14 @@ CLUSTER = [
     wl.LSTM_T80.scaled(name="lstm_bf16", dtype="bf16", layers=2, T=12, B=150, in_dim=40,
                        hidden=70, h0_std=0.5, c0_std=0.5),
     wl.GRU_3L.scaled(bidir=True, layers=2, T=15, B=140, in_dim=24, hidden=40, varlen=(1, 15)),
+    # widths whose units split evenly over the cluster (4 and 8 per CTA):
+    # several batch slices, variable lengths, both directions
+    wl.LSTM_T80.scaled(name="lstm_q4", T=13, B=37, in_dim=30, hidden=64, varlen=(1, 13),
+                       h0_std=0.5, c0_std=0.5),
+    wl.GRU_3L.scaled(name="gru_q8", dtype="f32", layers=2, bidir=True, T=10, B=20, in_dim=12,
+                     hidden=128, varlen=(2, 10)),
+    wl.LSTM_T80.scaled(name="lstm_bf16_q8", dtype="bf16", layers=2, T=9, B=60, in_dim=16,
+                       hidden=128),
 ]
 
 
