@@ -16,6 +16,7 @@ fp64 CPU oracle on the host cores instead (the only baseline this method has).
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import math
 import os
@@ -557,15 +558,21 @@ def run_ours(args, spec, rank, local, ws):
     dist_barrier()
     torch.cuda.synchronize(dev)
     clocks.start()
+    # no garbage-collector pass while the host enqueues the timed work
+    gc.collect()
+    gc.disable()
     t_wall = time.perf_counter()
     n_launch = 0
-    for i in range(args.steps):
-        flush_l2(flush)
-        evs[i][0].record(stream)
-        step()
-        evs[i][1].record(stream)
-        n_launch += launches()
-    torch.cuda.synchronize(dev)
+    try:
+        for i in range(args.steps):
+            flush_l2(flush)
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+            n_launch += launches()
+        torch.cuda.synchronize(dev)
+    finally:
+        gc.enable()
     wall = time.perf_counter() - t_wall
     dist_barrier()
     clk = clocks.stop()
@@ -711,11 +718,18 @@ def run_e2e(args, spec, e2e_io, status, keep, dev, stream, local, device_ms):
         torch.cuda.synchronize(dev)
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(e2e_steps)]
-        for i in range(e2e_steps):
-            evs[i][0].record(stream)
-            host_call()
-            evs[i][1].record(stream)
-        torch.cuda.synchronize(dev)
+        gc.collect()
+        gc.disable()
+        try:
+            t_host = time.perf_counter()
+            for i in range(e2e_steps):
+                evs[i][0].record(stream)
+                host_call()
+                evs[i][1].record(stream)
+            t_host = time.perf_counter() - t_host
+            torch.cuda.synchronize(dev)
+        finally:
+            gc.enable()
         per = [a.elapsed_time(b) for a, b in evs]
         e2e_ms = dist_max(sum(per) / e2e_steps, dev)
         e2e_value = dist_sum(units(spec, None), dev) / (e2e_ms / 1e3)
@@ -735,6 +749,9 @@ def run_e2e(args, spec, e2e_io, status, keep, dev, stream, local, device_ms):
             # shows here and in the list)
             "ms_per_step_median": round(sorted(per)[len(per) // 2], 4),
             "warmup_calls": warm,
+            # host time to issue the calls: well under the device time means
+            # the host ran ahead of the GPU
+            "host_issue_ms_per_step": round(t_host * 1e3 / e2e_steps, 3),
             "device_ms_per_step": round(device_ms, 4),
             "link": link,
             "h2d_ms_alone": round(h2d / (link["h2d_gbs"] * 1e9) * 1e3, 3),
