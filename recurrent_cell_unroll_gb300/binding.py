@@ -440,6 +440,7 @@ class RNN:
         if bidirectional:
             c |= RCU_BIDIR
         self.cell, self.layers, self.hidden, self.proj = cell, layers, hidden, proj
+        self.in_dim = in_dim
         self.D = 2 if bidirectional else 1
         self.Hout = proj if proj > 0 else hidden
         self.h = rnn_create(c, layers, in_dim, hidden, proj, RCU_BF16 if dtype == "bf16" else RCU_F32)
@@ -456,8 +457,24 @@ class RNN:
             rnn_set_weights(self.h, layer, d, t["w_ih"], t["w_hh"], t.get("b_ih"), t.get("b_hh"),
                             t.get("w_hr"), stream)
 
-    def forward(self, x, lengths=None, h0=None, c0=None, out=None, stream=None):
+    def _shapes(self, x, lengths=None, h0=None, c0=None, **seq):
+        """The C ABI takes plain pointers and reads every tensor at the size
+        the handle and (T, B) imply: a tensor of another shape is an error
+        here, before any pointer crosses."""
+        if x.dim() != 3 or x.shape[2] != self.in_dim:
+            raise ValueError(f"x must be [T, B, {self.in_dim}], got {tuple(x.shape)}")
         T, B, _ = x.shape
+        LD = self.layers * self.D
+        want = {"lengths": (B,), "h0": (LD, B, self.Hout), "c0": (LD, B, self.hidden)}
+        want.update({k: (T, B, self.D * self.Hout) if k in ("dy", "out") else
+                     (LD, B, self.Hout if k == "dh_n" else self.hidden) for k in seq})
+        for k, t in dict(lengths=lengths, h0=h0, c0=c0, **seq).items():
+            if t is not None and tuple(t.shape) != want[k]:
+                raise ValueError(f"{k} must be {list(want[k])}, got {list(t.shape)}")
+        return T, B
+
+    def forward(self, x, lengths=None, h0=None, c0=None, out=None, stream=None):
+        T, B = self._shapes(x, lengths, h0, c0, out=out)
         dev = x.device
         y = out if out is not None else torch.empty((T, B, self.D * self.Hout), device=dev)
         hn = torch.empty((self.layers * self.D, B, self.Hout), device=dev)
@@ -470,7 +487,8 @@ class RNN:
         """Gradients of a loss with dL/dy = dy (and dL/dh_n, dL/dc_n) through
         the forward on x (with lengths: int32 [B] on the device): returns (dx, dh0, dc0 or None, weight grads as a
         list over layers of dicts w_ih, w_hh, b_ih, b_hh)."""
-        T, B, in_dim = x.shape
+        T, B = self._shapes(x, lengths, h0, c0, dy=dy, dh_n=dh_n, dc_n=dc_n)
+        in_dim = x.shape[2]
         dev = x.device
         dx = torch.empty_like(x)
         LD = self.layers * self.D

@@ -1308,17 +1308,28 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
       dhnl = nullptr;
       ++launches;
     }
-    // h_{t-1} for t = 0 .. T-1
-    if (h0) CU(cudaMemcpyAsync(hp, h0 + (size_t)i * B * Ho, (size_t)B * Ho * 4, cudaMemcpyDeviceToDevice, s));
-    else CU(cudaMemsetAsync(hp, 0, (size_t)B * Ho * 4, s));
-    if (T > 1)
-      CU(cudaMemcpyAsync(hp + (size_t)B * Ho, Y, (size_t)(T - 1) * B * Ho * 4,
-                         cudaMemcpyDeviceToDevice, s));
-    // pre-activations of every step
-    const bool tcr = tcg && tc_gemm_supported(K, G) && tc_gemm_supported(Ho, G);
     // the tcgen05 GRU reverse-time kernel (below) activates the gates itself
     // and reads its per-step inputs transposed
     const bool tcb = tcg && cell == RCU_GRU && P == 0 && !lengths && tc_bwd_supported(H, B, h->nsm);
+    // h_{t-1} for t = 0 .. T-1 as one [M][Ho] sequence: h0's rows, then Y's
+    // first T-1 steps.  The tcgen05 path reads the two parts where they are
+    // (its bf16 rows and transposes are written from h0 and Y directly) and
+    // copies them only if a later step needs the sequence itself.
+    const float *h0i = h0 ? h0 + (size_t)i * B * Ho : nullptr;
+    bool hp_ready = false;
+    auto ensure_hp = [&]() -> cudaError_t {
+      if (hp_ready) return cudaSuccess;
+      hp_ready = true;
+      cudaError_t e0 = h0i ? cudaMemcpyAsync(hp, h0i, (size_t)B * Ho * 4, cudaMemcpyDeviceToDevice, s)
+                           : cudaMemsetAsync(hp, 0, (size_t)B * Ho * 4, s);
+      if (e0 == cudaSuccess && T > 1)
+        e0 = cudaMemcpyAsync(hp + (size_t)B * Ho, Y, (size_t)(T - 1) * B * Ho * 4,
+                             cudaMemcpyDeviceToDevice, s);
+      return e0;
+    };
+    if (!tcb) CU(ensure_hp());
+    // pre-activations of every step
+    const bool tcr = tcg && tc_gemm_supported(K, G) && tc_gemm_supported(Ho, G);
     int nl = 0;  // kernels launched by this (layer, direction)
     h->begin("bwd_recompute_gemm", s);
     cudaError_t e = cudaSuccess;
@@ -1331,13 +1342,18 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
         e = launch_tc_gemm((const __nv_bfloat16 *)h->wih[l].p + (size_t)d * G * ldk, ldk, Xb, ldk,
                            (const float *)lw.bih_plain.p, zin, ldm8, G, nullptr, M, K, h->nsm, s,
                            err, (uint64_t)h->timeout_ns, true);
-      if (e == cudaSuccess) e = launch_convert_rows_bf16(hp, M, Ho, Ho, Hb, ldo, s);
+      // bf16 h_{t-1} rows: h0's (or zeros), then Y's first T-1 steps
+      if (e == cudaSuccess)
+        e = h0i ? launch_convert_rows_bf16(h0i, B, Ho, Ho, Hb, ldo, s)
+                : cudaMemsetAsync(Hb, 0, (size_t)B * ldo * 2, s);
+      if (e == cudaSuccess && T > 1)
+        e = launch_convert_rows_bf16(Y, M - B, Ho, Ho, Hb + (size_t)B * ldo, ldo, s);
       if (e == cudaSuccess)
         e = launch_convert_rows_bf16((const float *)lw.whh_plain.p, G, Ho, ldo, Wb, ldo, s);
       if (e == cudaSuccess)
         e = launch_tc_gemm(Wb, ldo, Hb, ldo, (const float *)lw.bhh_plain.p, zh, ldm8, G, nullptr,
                            M, Ho, h->nsm, s, err, (uint64_t)h->timeout_ns, true);
-      nl += 5;
+      nl += 4 + (h0i ? 1 : 0) + (T > 1 ? 1 : 0);
     } else if (tcr) {
       // the forward's own operands: bf16 x (or the previous layer's bf16
       // output), bf16 h_{t-1}, the bf16 weights
@@ -1415,10 +1431,19 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
       // h_{t-1}^T and dy^T for the kernel (and with the weight GEMMs on the
       // tensor cores, H_prev^T in bf16 from the same pass)
       h->begin("bwd_transpose", s);
-      e = launch_transpose_dual(hp, M, Ho, Ho, HPT, tw ? T4b : nullptr, ldm8, s);
+      // (columns [0, B) from h0, or zeros; columns [B, M) from Y)
+      if (h0i) {
+        e = launch_transpose_dual(h0i, B, Ho, Ho, HPT, tw ? T4b : nullptr, ldm8, s);
+      } else {
+        e = cudaMemset2DAsync(HPT, (size_t)ldm8 * 4, 0, (size_t)B * 4, Ho, s);
+        if (e == cudaSuccess && tw)
+          e = cudaMemset2DAsync(T4b, (size_t)ldm8 * 2, 0, (size_t)B * 2, Ho, s);
+      }
+      if (e == cudaSuccess && T > 1)
+        e = launch_transpose_dual(Y, M - B, Ho, Ho, HPT + B, tw ? T4b + B : nullptr, ldm8, s);
       if (e == cudaSuccess) e = launch_transpose_dual(rec_dy, M, Ho, Ho, DYT, nullptr, ldm8, s);
       h->end(s);
-      nl += 2;
+      nl += 1 + (h0i ? 1 : 0) + (T > 1 ? 1 : 0);
       h->begin("bwd_recurrent_tc", s);
       if (e == cudaSuccess)
         e = launch_transpose_bf16((const float *)lw.whh_plain.p, G, H, ldo, WTh, g8, s);
@@ -1509,7 +1534,8 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
       if (e == cudaSuccess) e = launch_transpose_bf16(hp, M, Ho, Ho, T4b, ldm8, s);
       nl += cell == RCU_GRU ? 4 : 3;
     } else {
-      e = launch_transpose(DA, M, G, G, T1, M, s);
+      e = ensure_hp();
+      if (e == cudaSuccess) e = launch_transpose(DA, M, G, G, T1, M, s);
       if (e == cudaSuccess) e = launch_transpose(X, M, K, K, T2, M, s);
       if (e == cudaSuccess && cell == RCU_GRU) e = launch_transpose(DR, M, G, G, T3, M, s);
       if (e == cudaSuccess) e = launch_transpose(hp, M, Ho, Ho, T4, M, s);

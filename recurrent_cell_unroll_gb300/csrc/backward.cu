@@ -599,6 +599,28 @@ __global__ void convert_rows_kernel(const float *__restrict__ in, int R, int C, 
       out[(size_t)r * ldo + c] = __float2bfloat16_rn(in[(size_t)r * ldi + c]);
 }
 
+// the same, 8 columns per thread: two 16-byte loads, one 16-byte store
+// (C, ldi and ldo multiples of 8, both pointers 16-byte aligned)
+__global__ void convert_rows8_kernel(const float *__restrict__ in, int R, int C8, int ldi,
+                                     __nv_bfloat16 *__restrict__ out, int ldo) {
+  const size_t n = (size_t)R * C8;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = i / (size_t)C8;
+    const int c = (int)(i - r * (size_t)C8) * 8;
+    const float4 a = __ldcs(reinterpret_cast<const float4 *>(in + r * ldi + c));
+    const float4 b = __ldcs(reinterpret_cast<const float4 *>(in + r * ldi + c + 4));
+    const __nv_bfloat162 v0 = __floats2bfloat162_rn(a.x, a.y), v1 = __floats2bfloat162_rn(a.z, a.w),
+                         v2 = __floats2bfloat162_rn(b.x, b.y), v3 = __floats2bfloat162_rn(b.z, b.w);
+    uint4 o;
+    o.x = *reinterpret_cast<const uint32_t *>(&v0);
+    o.y = *reinterpret_cast<const uint32_t *>(&v1);
+    o.z = *reinterpret_cast<const uint32_t *>(&v2);
+    o.w = *reinterpret_cast<const uint32_t *>(&v3);
+    *reinterpret_cast<uint4 *>(out + r * ldo + c) = o;
+  }
+}
+
 // deterministic column sums of an M x N row-major matrix: chunk partials,
 // then the chunks summed in order
 constexpr int CS_ROWS = 1024;
@@ -874,6 +896,16 @@ cudaError_t launch_transpose_dual(const float *in, int R, int C, int ldi, float 
 cudaError_t launch_convert_rows_bf16(const float *in, int R, int C, int ldi, __nv_bfloat16 *out,
                                      int ldo, cudaStream_t s) {
   if (R <= 0 || C <= 0) return cudaSuccess;
+  if (C % 8 == 0 && ldi % 8 == 0 && ldo % 8 == 0 && (reinterpret_cast<uintptr_t>(in) & 15) == 0 &&
+      (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
+    int dev = 0, nsm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+    const size_t n = (size_t)R * (C / 8);
+    const int grid = (int)std::min<size_t>((n + 255) / 256, (size_t)std::max(nsm, 1) * 8);
+    convert_rows8_kernel<<<grid, 256, 0, s>>>(in, R, C / 8, ldi, out, ldo);
+    return cudaGetLastError();
+  }
   convert_rows_kernel<<<std::min(R, 65535), 256, 0, s>>>(in, R, C, ldi, out, ldo);
   return cudaGetLastError();
 }

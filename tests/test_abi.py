@@ -67,6 +67,26 @@ def test_binding_rejects_host_tensors():
         binding._dev(torch.zeros(3))
 
 
+def test_binding_checks_tensor_shapes_before_the_call():
+    """The C ABI reads each buffer at the size (T, B) and the handle imply, so
+    the wrapper refuses a tensor of any other shape (a bidirectional net
+    wants dy [T, B, 2*Hout])."""
+    from types import SimpleNamespace
+    net = SimpleNamespace(in_dim=16, layers=2, D=2, Hout=32, hidden=32)
+    x = torch.zeros(5, 3, 16)
+    ok = dict(lengths=torch.zeros(3), h0=torch.zeros(4, 3, 32), c0=torch.zeros(4, 3, 32))
+    assert binding.RNN._shapes(net, x, **ok, dy=torch.zeros(5, 3, 64),
+                               dh_n=torch.zeros(4, 3, 32)) == (5, 3)
+    bad = [dict(dy=torch.zeros(5, 3, 32)), dict(h0=torch.zeros(2, 3, 32)),
+           dict(lengths=torch.zeros(4)), dict(out=torch.zeros(5, 3, 63)),
+           dict(dc_n=torch.zeros(4, 2, 32))]
+    for kw in bad:
+        with pytest.raises(ValueError):
+            binding.RNN._shapes(net, x, **kw)
+    with pytest.raises(ValueError):
+        binding.RNN._shapes(net, torch.zeros(5, 3, 15))
+
+
 def test_constants_match_header():
     """Every RCU_* value the binding names is the header's #define."""
     import re

@@ -133,6 +133,14 @@ BWD_BF16_SPECS = [
     # T*B = 4096 rows: the weight-gradient GEMMs (2 output tiles against
     # 64 K blocks) split K into 4 chunks summed in order
     wl.GRU_3L.scaled(T=64, B=64, in_dim=32, hidden=64, layers=2, h0_std=0.5),
+    # the tcgen05 reverse-time path reads h_{t-1} from h0 and the layer's
+    # output in place: no h0 (zero rows), both directions, a single step (h0
+    # alone), and an input width of 13 (fp32 weight-gradient GEMMs, which
+    # take the assembled h_{t-1} sequence)
+    wl.GRU_3L.scaled(T=6, B=40, in_dim=32, hidden=64, layers=2, h0_std=0.0),
+    wl.GRU_3L.scaled(T=5, B=24, in_dim=16, hidden=32, layers=2, bidir=True, h0_std=0.3),
+    wl.GRU_3L.scaled(T=1, B=16, in_dim=16, hidden=32, layers=1, h0_std=0.5),
+    wl.GRU_3L.scaled(T=5, B=20, in_dim=13, hidden=32, layers=1, h0_std=0.5),
 ]
 
 
@@ -146,8 +154,8 @@ def test_backward_bf16_parity(spec):
     states)."""
     inp = wl.make_rnn_inputs(spec, seed=13)
     g = torch.Generator().manual_seed(98)
-    L, B, Ho = spec.layers, spec.B, spec.Hout
-    dy = torch.randn((spec.T, B, Ho), generator=g)
+    L, D, B, Ho = spec.layers, spec.D, spec.B, spec.Hout
+    dy = torch.randn((spec.T, B, D * Ho), generator=g)
     dev = torch.device("cuda")
     net = binding.RNN.from_spec(spec)
     net.set_weights(inp["weights"])
@@ -164,10 +172,10 @@ def test_backward_bf16_parity(spec):
     tc_rec = spec.cell == "gru" and spec.varlen is None and spec.hidden % 32 == 0
     assert ("bwd_recurrent_tc" in net.profile()) == tc_rec, net.profile()
     ref = oracle.rnn_backward(_cell(spec), inp["x"], inp["weights"], dy, hidden=spec.hidden,
-                              proj=spec.proj, lengths=inp["lengths"], h0=inp["h0"],
-                              c0=inp["c0"], bf16_weights=True)
+                              proj=spec.proj, bidirectional=spec.bidir, lengths=inp["lengths"],
+                              h0=inp["h0"], c0=inp["c0"], bf16_weights=True)
     pairs = [("dx", dx, ref["dx"]), ("dh0", dh0, ref["dh0"])]
-    for i in range(L):
+    for i in range(L * D):
         for k in ("w_ih", "w_hh", "b_ih") + (("w_hr",) if spec.proj else ()):
             pairs.append((f"d{k}[{i}]", grads[i][k], ref["d" + k][i]))
     for name, got, want in pairs:
