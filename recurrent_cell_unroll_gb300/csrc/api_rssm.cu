@@ -278,8 +278,12 @@ static int rssm_backward_run(rcu_rssm_t h, bool with_actor, int T, int B, const 
   const int S = h->S, A = h->A, Hd = h->Hd, RH = h->RH, G = 3 * RH, SA = S + A, S2 = 2 * S;
   const int Hx = with_actor ? h->Hx : 0, SR = S + RH;
   const int M = T * B;
-  const int wmax = std::max(std::max(std::max(G, Hd), std::max(SA, S2)),
-                            with_actor ? std::max(SR, Hx) : 0);
+  // the weight-gradient groups' shapes (dZ width, Y width), for the scratch
+  // of their chunk partials: W1, W_ih, W_hh, W2, W3 (and the actor's Wa2, Wa1)
+  const WgradGroup wshape[7] = {{nullptr, Hd, nullptr, SA}, {nullptr, G, nullptr, Hd},
+                                {nullptr, G, nullptr, RH}, {nullptr, Hd, nullptr, RH},
+                                {nullptr, S2, nullptr, Hd}, {nullptr, A, nullptr, Hx},
+                                {nullptr, Hx, nullptr, SR}};
   size_t off = 0;
   auto take = [&](size_t n) { size_t r = off; off += (n + 63) & ~size_t(63); return r; };
   const size_t o_mean = take((size_t)M * S), o_std = take((size_t)M * S),
@@ -295,8 +299,7 @@ static int rssm_backward_run(rcu_rssm_t h, bool with_actor, int T, int B, const 
                o_w3t = take((size_t)Hd * S2), o_w2t = take((size_t)RH * Hd),
                o_whht = take((size_t)RH * G), o_wiht = take((size_t)Hd * G),
                o_w1st = take((size_t)S * Hd), o_w1at = take((size_t)std::max(A, 1) * Hd),
-               o_ta = take((size_t)M * wmax), o_tb = take((size_t)M * wmax),
-               o_csum = take(colsum_scratch_floats(M, wmax));
+               o_wg = take(wgrad_scratch_floats(wshape, with_actor ? 7 : 5, M));
   // actor only: its actions, inputs [s_{t-1}, h_{t-1}], layers and gradients
   const size_t na = with_actor ? 1 : 0;
   const size_t o_acts = take(na * M * A), o_xa = take(na * M * SR), o_ua = take(na * M * Hx),
@@ -313,8 +316,7 @@ static int rssm_backward_run(rcu_rssm_t h, bool with_actor, int T, int B, const 
   float *TQ = ws + o_tq, *THQ = ws + o_thq, *GH = ws + o_gh, *DHZ = ws + o_dhz, *TX = ws + o_tx,
         *CS = ws + o_cs;
   float *W3T = ws + o_w3t, *W2T = ws + o_w2t, *WhhT = ws + o_whht, *WihT = ws + o_wiht,
-        *W1sT = ws + o_w1st, *W1aT = ws + o_w1at, *TA = ws + o_ta, *TB = ws + o_tb,
-        *csum = ws + o_csum;
+        *W1sT = ws + o_w1st, *W1aT = ws + o_w1at, *WG = ws + o_wg;
   float *ACTS = ws + o_acts, *XA = ws + o_xa, *UA = ws + o_ua, *HA = ws + o_ha,
         *DACT = ws + o_dact, *DVA = ws + o_dva, *DHA = ws + o_dha, *TDHA = ws + o_tdha,
         *CSA = ws + o_csa, *GA = ws + o_ga, *Wa2T = ws + o_wa2t, *Wa1sT = ws + o_wa1st,
@@ -461,7 +463,8 @@ static int rssm_backward_run(rcu_rssm_t h, bool with_actor, int T, int B, const 
     CU(cudaMemcpyAsync(dactions, DACT, (size_t)M * A * 4, cudaMemcpyDeviceToDevice, s));
   else if (A > 0 && dactions)
     gemm(DU, Hd, W1aT, Hd, nullptr, dactions, A, M, A, Hd);
-  // ---- weight gradients: dW = dZ^T Y through K-contiguous transposes, db = column sums
+  // ---- weight gradients: dW = dZ^T Y and db = column sums of dZ, every
+  // layer's in one grouped pair of launches over the row-major activations
   const size_t nW[10] = {(size_t)Hd * SA, (size_t)Hd, (size_t)G * Hd, (size_t)G * RH, (size_t)G,
                          (size_t)G, (size_t)Hd * RH, (size_t)Hd, (size_t)S2 * Hd, (size_t)S2};
   size_t tot = 0;
@@ -470,31 +473,20 @@ static int rssm_backward_run(rcu_rssm_t h, bool with_actor, int T, int B, const 
   float *gp[10];
   gp[0] = (float *)h->gw.p;
   for (int i = 1; i < 10; ++i) gp[i] = gp[i - 1] + nW[i - 1];
-  struct WG { const float *dz; int nz; const float *y; int ny; float *dW; float *db; };
-  const WG wg[5] = {{DU, Hd, IN, SA, gp[0], gp[1]}, {DA, G, X, Hd, gp[2], gp[4]},
-                    {DR, G, HP, RH, gp[3], gp[5]}, {DV, Hd, bel, RH, gp[6], gp[7]},
-                    {DP, S2, Q, Hd, gp[8], gp[9]}};
-  for (const WG &w : wg) {
-    tr(w.dz, M, w.nz, w.nz, TA, M);
-    tr(w.y, M, w.ny, w.ny, TB, M);
-    gemm(TA, M, TB, M, nullptr, w.dW, w.ny, w.nz, w.ny, M);
-    if (e == cudaSuccess) e = launch_colsum(w.dz, M, w.nz, csum, w.db, s);
-    launches += 2;
-  }
+  WgradGroup wg[7] = {{DU, Hd, IN, SA, gp[0], gp[1]}, {DA, G, X, Hd, gp[2], gp[4]},
+                      {DR, G, HP, RH, gp[3], gp[5]}, {DV, Hd, bel, RH, gp[6], gp[7]},
+                      {DP, S2, Q, Hd, gp[8], gp[9]}};
+  int ng = 5;
   if (with_actor) {
     // dWa2 = dVa^T ha, dba2; dWa1 = dHa^T [s, h], dba1
     CU(h->gwa.ensure(((size_t)Hx * SR + Hx + (size_t)A * Hx + A) * 4));
     float *gWa1 = (float *)h->gwa.p, *gba1 = gWa1 + (size_t)Hx * SR, *gWa2 = gba1 + Hx,
           *gba2 = gWa2 + (size_t)A * Hx;
-    const WG wa[2] = {{DVA, A, HA, Hx, gWa2, gba2}, {DHA, Hx, XA, SR, gWa1, gba1}};
-    for (const WG &w : wa) {
-      tr(w.dz, M, w.nz, w.nz, TA, M);
-      tr(w.y, M, w.ny, w.ny, TB, M);
-      gemm(TA, M, TB, M, nullptr, w.dW, w.ny, w.nz, w.ny, M);
-      if (e == cudaSuccess) e = launch_colsum(w.dz, M, w.nz, csum, w.db, s);
-      launches += 2;
-    }
+    wg[ng++] = {DVA, A, HA, Hx, gWa2, gba2};
+    wg[ng++] = {DHA, Hx, XA, SR, gWa1, gba1};
   }
+  if (e == cudaSuccess) e = launch_wgrad(wg, ng, M, WG, s);
+  launches += 2;
   h->end(s);
   if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rssm_backward: gradients: %s", cudaGetErrorString(e));
   h->grads_ready = true;

@@ -197,6 +197,31 @@ cudaError_t launch_rssm_gru_grad(int t, int B, int RH, const float *dbeliefs, co
                                  const float *gh, float *dhz, const float *gates, const float *zh,
                                  const float *hp, float *DA, float *DR, cudaStream_t s);
 
+// Weight and bias gradients of up to WG_MAX_GROUPS layers over M rows in two
+// launches: dW [nz][ny] = dZ^T Y and db [nz] = column sums of dZ, from
+// row-major dZ [M][nz] and Y [M][ny]; the rows are summed in chunks of
+// WG_ROWS_PER_CHUNK whose partials are added in a fixed order.  scratch:
+// wgrad_scratch_floats(groups, n, M) floats.  (tile0 and off are set by the
+// launcher.)
+constexpr int WG_MAX_GROUPS = 8, WG_ROWS_PER_CHUNK = 160;
+struct WgradGroup {
+  const float *dz;
+  int nz;
+  const float *y;
+  int ny;
+  float *dW, *db;
+  int tile0;
+  size_t off;
+};
+struct WgradParams {
+  int ngroups, M, S, mchunk;
+  size_t total;
+  float *part;
+  WgradGroup g[WG_MAX_GROUPS];
+};
+size_t wgrad_scratch_floats(const WgradGroup *g, int n, int M);
+cudaError_t launch_wgrad(const WgradGroup *groups, int n, int M, float *scratch, cudaStream_t s);
+
 struct BwdRecArgs {
   int T, B, H, cell;
   const float *Whh;  // [nG*H][ldw]

@@ -124,7 +124,116 @@ __global__ void rssm_gru_grad_kernel(int t, int B, int RH, const float *__restri
   dhz[e] = dh * z;
 }
 
+// ---- weight gradients of several layers in two launches: for each group,
+// dW[o][k] = sum_m dZ[m][o] Y[m][k] and db[o] = sum_m dZ[m][o], read from the
+// row-major activations directly (Y is extended by a column of ones, whose
+// output column is db).  The rows are split into S chunks: the first kernel
+// writes each chunk's partial 64 x 64 tiles, the second sums the chunks in
+// order, so the result does not depend on timing.
+constexpr int WGT = 64, WGM = 32, WG_NT = 256;
+
+__global__ void __launch_bounds__(WG_NT) wgrad_partial_kernel(const WgradParams p) {
+  __shared__ __align__(16) float sdz[WGM][WGT];
+  __shared__ __align__(16) float sy[WGM][WGT];
+  int gi = 0;
+  while (gi + 1 < p.ngroups && (int)blockIdx.x >= p.g[gi + 1].tile0) ++gi;
+  const WgradGroup &g = p.g[gi];
+  const int tkn = ceil_div(g.ny + 1, WGT);
+  const int t = (int)blockIdx.x - g.tile0, o0 = (t / tkn) * WGT, k0 = (t % tkn) * WGT;
+  const int m0 = (int)blockIdx.y * p.mchunk, m1 = min(p.M, m0 + p.mchunk);
+  const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
+  const int lc = tid % WGT, lr = tid / WGT;  // loader: column, first row
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  const int o = o0 + lc, k = k0 + lc;
+  for (int mb = m0; mb < m1; mb += WGM) {
+#pragma unroll
+    for (int q = 0; q < WGM / 4; ++q) {
+      const int r = lr + 4 * q, m = mb + r;
+      const bool in = m < m1;
+      sdz[r][lc] = (in && o < g.nz) ? __ldg(g.dz + (size_t)m * g.nz + o) : 0.f;
+      sy[r][lc] = !in ? 0.f : k < g.ny ? __ldg(g.y + (size_t)m * g.ny + k) : (k == g.ny ? 1.f : 0.f);
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int mm = 0; mm < WGM; ++mm) {
+      const float4 a = *reinterpret_cast<const float4 *>(&sdz[mm][ty * 4]);
+      const float4 b = *reinterpret_cast<const float4 *>(&sy[mm][tx * 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+  // this chunk's partial tile: [o][ny + 1] rows of the group's slot
+  float *part = p.part + (size_t)blockIdx.y * p.total + g.off;
+  const int w = g.ny + 1;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int oo = o0 + ty * 4 + i;
+    if (oo >= g.nz) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int kk = k0 + tx * 4 + j;
+      if (kk < w) part[(size_t)oo * w + kk] = acc[i][j];
+    }
+  }
+}
+
+__global__ void wgrad_sum_kernel(const WgradParams p) {
+  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < p.total;
+       e += (size_t)gridDim.x * blockDim.x) {
+    float v = 0.f;
+    for (int c = 0; c < p.S; ++c) v += p.part[(size_t)c * p.total + e];
+    int gi = 0;
+    while (gi + 1 < p.ngroups && e >= p.g[gi + 1].off) ++gi;
+    const WgradGroup &g = p.g[gi];
+    const size_t l = e - g.off, w = (size_t)g.ny + 1;
+    const size_t o = l / w, k = l % w;
+    if (k < (size_t)g.ny) g.dW[o * g.ny + k] = v;
+    else g.db[o] = v;
+  }
+}
+
 }  // namespace
+
+size_t wgrad_scratch_floats(const WgradGroup *g, int n, int M) {
+  size_t tot = 0;
+  for (int i = 0; i < n; ++i) tot += (size_t)g[i].nz * (g[i].ny + 1);
+  return tot * (size_t)ceil_div(std::max(M, 1), WG_ROWS_PER_CHUNK);
+}
+
+cudaError_t launch_wgrad(const WgradGroup *groups, int n, int M, float *scratch, cudaStream_t s) {
+  if (n < 1 || n > WG_MAX_GROUPS || M < 1) return cudaErrorInvalidValue;
+  WgradParams p{};
+  p.ngroups = n;
+  p.M = M;
+  p.S = ceil_div(M, WG_ROWS_PER_CHUNK);
+  p.mchunk = WG_ROWS_PER_CHUNK;
+  p.part = scratch;
+  int tiles = 0;
+  size_t off = 0;
+  for (int i = 0; i < n; ++i) {
+    p.g[i] = groups[i];
+    if (p.g[i].nz < 1 || p.g[i].ny < 0) return cudaErrorInvalidValue;
+    p.g[i].tile0 = tiles;
+    p.g[i].off = off;
+    tiles += ceil_div(p.g[i].nz, WGT) * ceil_div(p.g[i].ny + 1, WGT);
+    off += (size_t)p.g[i].nz * (p.g[i].ny + 1);
+  }
+  p.total = off;
+  if (p.S > 65535) return cudaErrorInvalidValue;
+  wgrad_partial_kernel<<<dim3(tiles, p.S), WG_NT, 0, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  wgrad_sum_kernel<<<(unsigned)std::min<size_t>((off + 255) / 256, 4096), 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_rssm_inputs(int T, int B, int S, int A, const float *state0,
                                const float *states, const float *actions, float *in,

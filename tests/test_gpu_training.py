@@ -370,7 +370,8 @@ def test_rssm_profile_phases():
     assert binding.rssm_get_status(m.h) == 0
     for name in ("rssm_unroll", "rssm_bwd_recompute", "rssm_bwd_chain", "rssm_bwd_grads"):
         assert name in prof and prof[name][1] == 1 and prof[name][0] > 0.0, (name, prof)
-    assert m.launch_count() > 4 * spec.T
+    # (at least one launch in each of the four ranges)
+    assert m.launch_count() >= 4
     m.close()
 
 
