@@ -96,11 +96,29 @@ __device__ __forceinline__ __nv_bfloat16 cvt<__nv_bfloat16>(float v) {
   return __float2bfloat16_rn(v);
 }
 
-// One warp per (t, s) row; lanes stride the columns.
+// 8 consecutive values to 16-byte aligned storage
+__device__ __forceinline__ void store8(float *d, float4 a, float4 b) {
+  reinterpret_cast<float4 *>(d)[0] = a;
+  reinterpret_cast<float4 *>(d)[1] = b;
+}
+__device__ __forceinline__ void store8(__nv_bfloat16 *d, float4 a, float4 b) {
+  const __nv_bfloat162 v0 = __floats2bfloat162_rn(a.x, a.y), v1 = __floats2bfloat162_rn(a.z, a.w),
+                       v2 = __floats2bfloat162_rn(b.x, b.y), v3 = __floats2bfloat162_rn(b.z, b.w);
+  uint4 o;
+  o.x = *reinterpret_cast<const uint32_t *>(&v0);
+  o.y = *reinterpret_cast<const uint32_t *>(&v1);
+  o.z = *reinterpret_cast<const uint32_t *>(&v2);
+  o.w = *reinterpret_cast<const uint32_t *>(&v3);
+  *reinterpret_cast<uint4 *>(d) = o;
+}
+
+// One warp per (t, s) row; lanes stride the columns.  vec8: in and ld_out
+// multiples of 8, x and out 16-byte aligned (each lane then moves 8 values
+// per iteration with 16-byte accesses)
 template <typename OT>
 __global__ void pack_rows_kernel(const float *__restrict__ x, int T, int B, int in, Meta m,
-                                 OT *__restrict__ out, int ld_out) {
-  const int warps = blockDim.x / 32;
+                                 OT *__restrict__ out, int ld_out, int vec8) {
+  const int warps = blockDim.x / 32, lane = threadIdx.x % 32;
   const long long nrows = (long long)T * B;
   for (long long r = (long long)blockIdx.x * warps + threadIdx.x / 32; r < nrows;
        r += (long long)gridDim.x * warps) {
@@ -109,8 +127,14 @@ __global__ void pack_rows_kernel(const float *__restrict__ x, int T, int B, int 
     const int b = m.sorted_idx[s];
     const float *src = x + ((size_t)t * B + b) * in;
     OT *dst = out + (size_t)(m.step_off[t] + s) * ld_out;
-    for (int k = threadIdx.x % 32; k < in; k += 32) dst[k] = cvt<OT>(__ldg(src + k));
-    for (int k = in + threadIdx.x % 32; k < ld_out; k += 32) dst[k] = cvt<OT>(0.f);
+    if (vec8) {
+      for (int k = 8 * lane; k < in; k += 256)
+        store8(dst + k, __ldg(reinterpret_cast<const float4 *>(src + k)),
+               __ldg(reinterpret_cast<const float4 *>(src + k + 4)));
+    } else {
+      for (int k = lane; k < in; k += 32) dst[k] = cvt<OT>(__ldg(src + k));
+    }
+    for (int k = in + lane; k < ld_out; k += 32) dst[k] = cvt<OT>(0.f);
   }
 }
 
@@ -159,7 +183,10 @@ cudaError_t launch_meta(const int32_t *lengths, int B, int T, Meta m, int *err, 
 template <typename OT>
 cudaError_t launch_pack_rows(const float *x, int T, int B, int in, Meta m, OT *out, int ld_out,
                              cudaStream_t s) {
-  pack_rows_kernel<OT><<<grid_for((long long)T * B, 8), 256, 0, s>>>(x, T, B, in, m, out, ld_out);
+  const int vec8 = (in % 8 == 0 && ld_out % 8 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+                    (reinterpret_cast<uintptr_t>(out) & 15) == 0) ? 1 : 0;
+  pack_rows_kernel<OT><<<grid_for((long long)T * B, 8), 256, 0, s>>>(x, T, B, in, m, out, ld_out,
+                                                                     vec8);
   return cudaGetLastError();
 }
 template cudaError_t launch_pack_rows<float>(const float *, int, int, int, Meta, float *, int,
