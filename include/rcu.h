@@ -192,7 +192,7 @@ RCU_API int rnn_forward(rcu_rnn_t h, int T, int B, const float *x, const int32_t
  *     buffers with cudaMemcpyAsync.
  *   - lengths, h0, c0 are copied in, h_n, c_n copied out (small).
  *   - Chunked pipeline (RCU_ATTR_HOST_CHUNKS; automatic from 64 MB of x + y,
- *     one chunk per 64 steps, at most 8): for a unidirectional network
+ *     one chunk per 64 steps, at most 6): for a unidirectional network
  *     without projection or lengths, with page-locked x and y, the steps
  *     are run in chunks,
  *     each a forward of all layers from every layer's state after the

@@ -1117,9 +1117,9 @@ extern "C" int rnn_forward_host(rcu_rnn_t h, int T, int B, const float *x, const
   // LSTMP path takes an initial state through a separate fp32 term, which
   // would round differently from the recurrence it replaces), x and y
   // page-locked (so the copies are asynchronous); automatic for transfers of
-  // 64 MB and more, one chunk per 64 steps up to 8
+  // 64 MB and more, one chunk per 64 steps up to 6
   int n = h->host_chunks;
-  if (n == 0) n = x_bytes + y_bytes >= ((size_t)64 << 20) ? std::min(8, T / 64) : 1;
+  if (n == 0) n = x_bytes + y_bytes >= ((size_t)64 << 20) ? std::min(6, T / 64) : 1;
   n = std::min(n, T);
   if (n > 1 && h->D == 1 && h->P == 0 && !lengths && device_address(x) && device_address(y)) {
     h->plan_chunks = n;

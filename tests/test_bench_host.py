@@ -195,6 +195,8 @@ def test_host_chunk_boundaries_cover_every_step_once():
             steps = [b - a for a, b in zip(t, t[1:])]
             assert t[0] == 0 and t[-1] == T and min(steps) >= 1 and len(steps) <= 16
     assert _chunk_starts(512, 8) == [0, 19, 98, 177, 256, 335, 414, 493, 512]
+    # the automatic split of the 512-step GRU (one chunk per 64 steps, at most 6)
+    assert _chunk_starts(512, 6) == [0, 28, 142, 256, 370, 484, 512]
 
 
 def test_topology_cpu_affinity_parsing():
