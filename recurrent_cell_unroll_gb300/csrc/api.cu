@@ -1567,9 +1567,15 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     h->begin("bwd_colsum", s);
     // (with the kernel's per-batch-group sums, over nbg rows instead of M)
     if (e == cudaSuccess) e = launch_colsum(tcd ? BS : DA, tcd ? nbg : M, G, csum, gbih, s);
-    if (e == cudaSuccess)
-      e = launch_colsum(tcd ? BS + (size_t)nbg * G : DR, tcd ? nbg : M, G, csum, gbhh, s);
-    nl += 4;
+    if (!tcd && DR == DA) {
+      // LSTM: both biases enter the same pre-activations, db_hh = db_ih
+      if (e == cudaSuccess) e = cudaMemcpyAsync(gbhh, gbih, (size_t)G * 4, cudaMemcpyDeviceToDevice, s);
+      nl += 2;
+    } else {
+      if (e == cudaSuccess)
+        e = launch_colsum(tcd ? BS + (size_t)nbg * G : DR, tcd ? nbg : M, G, csum, gbhh, s);
+      nl += 4;
+    }
     h->end(s);
     h->begin("bwd_dx_gemm", s);
     if (e == cudaSuccess && dX) {

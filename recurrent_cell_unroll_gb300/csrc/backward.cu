@@ -754,42 +754,62 @@ __global__ void add_kernel(float *__restrict__ dst, const float *__restrict__ sr
 namespace {
 // out[s][b][c] = in[t][b][col0 + c] (row stride ldi), t = s, or reversed
 // within the row's length: t = len_b-1-s for s < len_b, t = s past it
+// V = 4: w, ldi and col0 multiples of 4 and both buffers 16-byte aligned
+// (each thread moves 4 consecutive columns)
+template <int V>
 __global__ void gather_steps_kernel(const float *__restrict__ in, int ldi, int col0, int w, int T,
                                     int B, int reverse, const int32_t *__restrict__ lengths,
                                     float *__restrict__ out) {
-  const size_t n = (size_t)T * B * w;
+  const int wv = w / V;
+  const size_t n = (size_t)T * B * wv;
   for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
        e += (size_t)gridDim.x * blockDim.x) {
-    const int c = (int)(e % w);
-    const size_t row = e / w;  // s * B + b
+    const int c = (int)(e % wv) * V;
+    const size_t row = e / wv;  // s * B + b
     const int sidx = (int)(row / B), b = (int)(row % B);
     // reversal within each row's own length; steps past it stay in place
     const int len = lengths ? clamp_len(lengths[b], T) : T;
     const int t = (reverse && sidx < len) ? len - 1 - sidx : sidx;
-    out[e] = in[((size_t)t * B + b) * ldi + col0 + c];
+    const float *src = in + ((size_t)t * B + b) * ldi + col0 + c;
+    if constexpr (V == 4)
+      *reinterpret_cast<float4 *>(out + row * w + c) = *reinterpret_cast<const float4 *>(src);
+    else
+      out[row * w + c] = *src;
   }
 }
 // out[t][b][:] = in[t][b][:] (+ dhn[b][:] at t = len_b - 1) for t < len_b, 0
-// past the row's end; out may equal in
+// past the row's end; out may equal in (V = 4 as above)
+template <int V>
 __global__ void mask_steps_kernel(const float *in, int w, int T, int B,
                                   const int32_t *__restrict__ lengths,
                                   const float *__restrict__ dhn, float *out) {
-  const size_t n = (size_t)T * B * w;
+  const int wv = w / V;
+  const size_t n = (size_t)T * B * wv;
   for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
        e += (size_t)gridDim.x * blockDim.x) {
-    const int c = (int)(e % w);
-    const size_t row = e / w;
+    const int c = (int)(e % wv) * V;
+    const size_t row = e / wv;
     const int t = (int)(row / B), b = (int)(row % B);
     const int len = clamp_len(lengths[b], T);
-    float v = 0.f;
+    float v[V];
+#pragma unroll
+    for (int q = 0; q < V; ++q) v[q] = 0.f;
     if (t < len) {
-      v = in[e];
-      if (dhn && t == len - 1) v += dhn[(size_t)b * w + c];
+#pragma unroll
+      for (int q = 0; q < V; ++q) v[q] = in[row * w + c + q];
+      if (dhn && t == len - 1)
+#pragma unroll
+        for (int q = 0; q < V; ++q) v[q] += dhn[(size_t)b * w + c + q];
     }
-    out[e] = v;
+    if constexpr (V == 4)
+      *reinterpret_cast<float4 *>(out + row * w + c) = make_float4(v[0], v[1], v[2], v[3]);
+    else
+      out[row * w + c] = v[0];
   }
 }
 }  // namespace
+
+static bool al16(const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; }
 
 cudaError_t launch_gather_steps(const float *in, int ldi, int col0, int w, int T, int B,
                                 bool reverse, const int32_t *lengths, float *out,
@@ -797,8 +817,12 @@ cudaError_t launch_gather_steps(const float *in, int ldi, int col0, int w, int T
   const size_t n = (size_t)T * B * w;
   if (n == 0) return cudaSuccess;
   const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, 65535u * 8);
-  gather_steps_kernel<<<blocks, 256, 0, s>>>(in, ldi, col0, w, T, B, reverse ? 1 : 0, lengths,
-                                             out);
+  if (w % 4 == 0 && ldi % 4 == 0 && col0 % 4 == 0 && al16(in) && al16(out))
+    gather_steps_kernel<4><<<blocks, 256, 0, s>>>(in, ldi, col0, w, T, B, reverse ? 1 : 0,
+                                                  lengths, out);
+  else
+    gather_steps_kernel<1><<<blocks, 256, 0, s>>>(in, ldi, col0, w, T, B, reverse ? 1 : 0,
+                                                  lengths, out);
   return cudaGetLastError();
 }
 
@@ -808,7 +832,10 @@ cudaError_t launch_mask_steps(const float *in, int w, int T, int B, const int32_
   if (n == 0) return cudaSuccess;
   if (!lengths) return cudaErrorInvalidValue;
   const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, 65535u * 8);
-  mask_steps_kernel<<<blocks, 256, 0, s>>>(in, w, T, B, lengths, dhn, out);
+  if (w % 4 == 0 && al16(in) && al16(out) && (!dhn || al16(dhn)))
+    mask_steps_kernel<4><<<blocks, 256, 0, s>>>(in, w, T, B, lengths, dhn, out);
+  else
+    mask_steps_kernel<1><<<blocks, 256, 0, s>>>(in, w, T, B, lengths, dhn, out);
   return cudaGetLastError();
 }
 
