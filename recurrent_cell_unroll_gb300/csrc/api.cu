@@ -1229,6 +1229,17 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
                o_ctl = take((size_t)std::max(64, tc_bwd_counters(B))),
                // split-K partials of the tensor-core weight-gradient GEMMs (at most 4 chunks)
                o_wsk = take(h->dtype == RCU_BF16 ? 4 * (size_t)G * round_up(std::max(kmax, Ho), 4) : 0);
+  // a bidirectional layer whose two directions' reverse-time recurrences
+  // share one launch: the second direction's copies of the pieces that live
+  // from its recompute to its recurrence
+  const size_t n2 = D > 1 ? 1 : 0;
+  const size_t o_zin1 = take(n2 * G * ldm8), o_zh1 = take(n2 * G * ldm8),
+               o_cs1 = take(n2 * (cell == RCU_LSTM ? TBH : 0)), o_da1 = take(n2 * TBG),
+               o_dr1 = take(n2 * (cell == RCU_GRU ? TBG : 0)), o_hp1 = take(n2 * TBO),
+               o_dym1 = take(n2 * (lengths ? TBO : 0)),
+               o_cr1 = take(n2 * (cell == RCU_LSTM && h->cclip ? TBH : 0)),
+               o_yd1 = take(n2 * TBO), o_dyd1 = take(n2 * TBO),
+               o_ctl1 = take(n2 * std::max(64, tc_bwd_counters(B)));
   CU(h->bw.ensure(off * 4));
   float *wsf = (float *)h->bw.p;
   float *keep = wsf + o_keep, *hp = wsf + o_hp, *zin = wsf + o_zin, *zh = wsf + o_zh;
@@ -1245,6 +1256,15 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
   float *CR = (cell == RCU_LSTM && h->cclip) ? wsf + o_cr : nullptr;
   float *BS = wsf + o_bs, *HPT = wsf + o_hpt, *DYT = wsf + o_dyt, *WSK = wsf + o_wsk;
   unsigned *ctr = (unsigned *)(wsf + o_ctl);
+  float *const zin_0 = zin, *const zh_0 = zh, *const cs_0 = cs, *const DA_0 = DA, *const DR_0 = DR,
+              *const hp_0 = hp, *const DYM_0 = DYM, *const CR_0 = CR;
+  unsigned *const ctr_0 = ctr;
+  float *const zin_1 = wsf + o_zin1, *const zh_1 = wsf + o_zh1,
+              *const cs_1 = cell == RCU_LSTM ? wsf + o_cs1 : nullptr, *const DA_1 = wsf + o_da1,
+              *const DR_1 = cell == RCU_GRU ? wsf + o_dr1 : DA_1, *const hp_1 = wsf + o_hp1,
+              *const DYM_1 = wsf + o_dym1, *const CR_1 = CR ? wsf + o_cr1 : nullptr,
+              *const YD_1 = wsf + o_yd1, *const DYD_1 = wsf + o_dyd1;
+  unsigned *const ctr_1 = (unsigned *)(wsf + o_ctl1);
   // bf16 handles: the backward's GEMMs run on the tensor cores like the
   // forward's, on operands rounded to bf16 (the precision of every forward
   // MMA operand: x, h, W) with fp32 accumulation.  fp32 handles, and
@@ -1289,8 +1309,20 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
   // reverse direction's sequences are time-reversed copies, so it is an
   // ordinary forward recurrence): X [M][K], its output sequence Y [M][Ho],
   // dY [M][Ho]; writes dX [M][K] (may be NULL) and the weight gradients.
+  // the tcgen05 GRU reverse-time kernel (below) activates the gates itself
+  // and reads its per-step inputs transposed
+  const bool tcb_all = tcg && cell == RCU_GRU && P == 0 && !lengths && tc_bwd_supported(H, B, h->nsm);
+  // stage 0: everything; 1: up to the reverse-time recurrence, whose
+  // arguments go to *rec_out (not launched); 2: what follows it.  slot 1: the
+  // second direction's copies of the pieces that live across the recurrence.
   auto run_dir = [&](int l, int d, const float *X, int K, const float *Y, const float *dYdir,
-                     float *dX) -> int {
+                     float *dX, int stage = 0, int slot = 0, BwdRecArgs *rec_out = nullptr) -> int {
+    float *const zin = slot ? zin_1 : zin_0, *const zh = slot ? zh_1 : zh_0,
+                *const cs = slot ? cs_1 : cs_0, *const DA = slot ? DA_1 : DA_0,
+                *const DR = slot ? DR_1 : DR_0, *const hp = slot ? hp_1 : hp_0,
+                *const DYM = slot ? DYM_1 : DYM_0, *const CR = slot ? CR_1 : CR_0;
+    unsigned *const ctr = slot ? ctr_1 : ctr_0;
+    const bool pre = stage != 2;
     const int i = l * D + d, ldk = round_up(K, 8);
     const LayerDirW &lw = h->lw[(size_t)i];
     // fp32 W_ih (bf16 handles: of the rounded weights the forward used)
@@ -1300,23 +1332,23 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     // variable lengths: dy zero past each row's end, dh_n added at its last
     // step (h_n is the state there); the recurrence then carries no dh_n
     if (lengths) {
-      h->begin("bwd_mask", s);
-      cudaError_t e = launch_mask_steps(dYdir, Ho, T, B, lengths, dhnl, DYM, s);
-      h->end(s);
-      if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: mask: %s", cudaGetErrorString(e));
+      if (pre) {
+        h->begin("bwd_mask", s);
+        cudaError_t e = launch_mask_steps(dYdir, Ho, T, B, lengths, dhnl, DYM, s);
+        h->end(s);
+        if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: mask: %s", cudaGetErrorString(e));
+        ++launches;
+      }
       dYdir = DYM;
       dhnl = nullptr;
-      ++launches;
     }
-    // the tcgen05 GRU reverse-time kernel (below) activates the gates itself
-    // and reads its per-step inputs transposed
-    const bool tcb = tcg && cell == RCU_GRU && P == 0 && !lengths && tc_bwd_supported(H, B, h->nsm);
+    const bool tcb = tcb_all;
     // h_{t-1} for t = 0 .. T-1 as one [M][Ho] sequence: h0's rows, then Y's
     // first T-1 steps.  The tcgen05 path reads the two parts where they are
     // (its bf16 rows and transposes are written from h0 and Y directly) and
     // copies them only if a later step needs the sequence itself.
     const float *h0i = h0 ? h0 + (size_t)i * B * Ho : nullptr;
-    bool hp_ready = false;
+    bool hp_ready = !pre;  // (stage 2: filled by stage 1)
     auto ensure_hp = [&]() -> cudaError_t {
       if (hp_ready) return cudaSuccess;
       hp_ready = true;
@@ -1327,13 +1359,14 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
                              cudaMemcpyDeviceToDevice, s);
       return e0;
     };
-    if (!tcb) CU(ensure_hp());
+    if (!tcb && pre) CU(ensure_hp());
     // pre-activations of every step
     const bool tcr = tcg && tc_gemm_supported(K, G) && tc_gemm_supported(Ho, G);
     int nl = 0;  // kernels launched by this (layer, direction)
-    h->begin("bwd_recompute_gemm", s);
+    if (pre) h->begin("bwd_recompute_gemm", s);
     cudaError_t e = cudaSuccess;
-    if (tcb) {
+    if (!pre) {
+    } else if (tcb) {
       // (W_ih X^T + b_ih) and (W_hh H_prev^T + b_hh): the same products with
       // the operands' roles swapped, the biases added per output row
       __nv_bfloat16 *Xb = bws + b_x, *Hb = bws + b_hp, *Wb = bws + b_whh;
@@ -1377,9 +1410,9 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
         e = gemm_f32(h, hp, Ho, (const float *)lw.whh_plain.p, ldo, (const float *)lw.bhh_plain.p,
                      zh, G, M, nullptr, G, Ho, s, err, &nl);
     }
-    h->end(s);
+    if (pre) h->end(s);
     const float *c0l = c0 ? c0 + (size_t)i * B * H : nullptr;
-    if (!tcb) {
+    if (!tcb && pre) {
       h->begin("bwd_prep", s);
       if (e == cudaSuccess)
         e = launch_bwd_prep(T, B, H, cell, zin, zh, c0l, cs, ms, s, CR, h->cclip_lo, h->cclip_hi);
@@ -1411,7 +1444,7 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     // the reverse-time recurrence: on the tensor cores for the GRU of a bf16
     // handle over fixed-length rows (W_hh^T dR_{t+1} with bf16 operands, as
     // every MMA of its forward), else the FFMA kernel
-    CU(cudaMemsetAsync(ctr, 0, (size_t)std::max(64, tc_bwd_counters(B)) * 4, s));
+    if (pre) CU(cudaMemsetAsync(ctr, 0, (size_t)std::max(64, tc_bwd_counters(B)) * 4, s));
     DevBuf &g = h->gw[(size_t)i];
     CU(g.ensure(((size_t)G * K + (size_t)G * Ho + 2 * (size_t)G + (size_t)P * H) * 4));
     float *gWih = (float *)g.p, *gWhh = gWih + (size_t)G * K, *gbih = gWhh + (size_t)G * Ho,
@@ -1488,7 +1521,7 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     a.dc0 = dc0 ? dc0 + (size_t)i * B * H : nullptr;
     a.ctr = ctr; a.err = err; a.timeout_ns = (uint64_t)h->timeout_ns;
     a.drop_arrival = h->drop_arrival == 2 && l == L - 1 && d == 0;
-    if (!tcb && h->trace && l == 0 && d == 0) {
+    if (!tcb && pre && h->trace && l == 0 && d == 0) {
       // the last reverse-time launch (layer 0) replaces the forward's stamps
       const size_t rows = (size_t)T + 1;
       CU(h->trace_buf.ensure(rows * 16 * 8));
@@ -1496,7 +1529,12 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
       h->trace_T = (int)rows;
       a.trace = (unsigned long long *)h->trace_buf.p;
     }
-    if (!tcb) {
+    if (!tcb && stage == 1) {  // launched with the other direction's
+      if (rec_out) *rec_out = a;
+      launches += nl;
+      return RCU_OK;
+    }
+    if (!tcb && stage == 0) {
       h->begin("bwd_recurrent", s);
       e = launch_bwd_rec(a, h->nsm, s);
       h->end(s);
@@ -1615,8 +1653,41 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
     const float *Yl = keep + (size_t)l * TBY;
     float *dXl = l == 0 ? dx : (dYcur == dYa ? dYb : dYa);
     if (l > 0 && !dXl) return fail(RCU_ERR_INVALID, "rnn_backward: internal");
+    // both directions' reverse-time recurrences in one launch, each on half
+    // of the SMs (FFMA kernel, no projection), when that plan fits
+    const bool conc = D == 2 && P == 0 && !tcb_all &&
+                      bwd_units_per_cta(H, B, nG, h->nsm / 2) >= 1;
     if (D == 1) {
       if (int r = run_dir(l, 0, Xl, K, Yl, dYcur, dXl)) return r;
+    } else if (conc) {
+      h->begin("bwd_reorder", s);
+      cudaError_t e = launch_gather_steps(Yl, DHo, 0, Ho, T, B, false, lengths, YD, s);
+      if (e == cudaSuccess) e = launch_gather_steps(dYcur, DHo, 0, Ho, T, B, false, lengths, DYD, s);
+      if (e == cudaSuccess) e = launch_gather_steps(Yl, DHo, Ho, Ho, T, B, true, lengths, YD_1, s);
+      if (e == cudaSuccess)
+        e = launch_gather_steps(dYcur, DHo, Ho, Ho, T, B, true, lengths, DYD_1, s);
+      if (e == cudaSuccess) e = launch_gather_steps(Xl, K, 0, K, T, B, true, lengths, XR, s);
+      h->end(s);
+      if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: reorder: %s", cudaGetErrorString(e));
+      launches += 5;
+      BwdRecArgs a0{}, a1{};
+      if (int r = run_dir(l, 0, Xl, K, YD, DYD, dXl, 1, 0, &a0)) return r;
+      if (int r = run_dir(l, 1, XR, K, YD_1, DYD_1, dXl ? DXR : nullptr, 1, 1, &a1)) return r;
+      h->begin("bwd_recurrent", s);
+      e = launch_bwd_rec(a0, h->nsm, s, &a1);
+      h->end(s);
+      if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: recurrence: %s", cudaGetErrorString(e));
+      launches += 1;
+      if (int r = run_dir(l, 0, Xl, K, YD, DYD, dXl, 2, 0)) return r;
+      if (int r = run_dir(l, 1, XR, K, YD_1, DYD_1, dXl ? DXR : nullptr, 2, 1)) return r;
+      if (dXl) {  // dX of the layer input: the forward one plus the reversed backward one
+        h->begin("bwd_reorder", s);
+        e = launch_gather_steps(DXR, K, 0, K, T, B, true, lengths, TMP, s);
+        if (e == cudaSuccess) e = launch_add(dXl, TMP, (size_t)M * K, s);
+        h->end(s);
+        if (e != cudaSuccess) return fail(RCU_ERR_CUDA, "rnn_backward: reorder: %s", cudaGetErrorString(e));
+        launches += 2;
+      }
     } else {
       for (int d = 0; d < 2; ++d) {
         // direction d's sequences in its processing order

@@ -118,6 +118,7 @@ struct BwdParams {
   int NB;             // staging buffers (chunks in flight: NB - 1)
   int KP, Gh;         // CTAs splitting K (1 or 2); K columns each holds
   int BS, NUG;        // batch rows per CTA; unit groups (CTA = batch group x unit group)
+  int per;            // CTAs of this problem (batch groups x unit groups)
   const float *Whh;   // [nG*H][ldw], PyTorch row order
   int ldw;
   const float *gates; // [T*B][G] activated gates
@@ -155,7 +156,7 @@ __device__ __forceinline__ void rstamp(const BwdParams &p, int s, int slot) {
 // partial sums of the other CTA's units into that CTA's shared memory
 // (st.async, counted on its mbarrier).
 template <int KP>
-__device__ __forceinline__ void bwd_rec_body(const BwdParams &p) {
+__device__ __forceinline__ void bwd_rec_body(const BwdParams &p, const int bid) {
   extern __shared__ __align__(16) float sm[];
   __shared__ uint64_t xbar;       // KP = 2: the peer's partial sums of this CTA's units
   __shared__ unsigned peer_sent;  // KP = 2: steps the peer sent (stored by the peer at exit)
@@ -170,7 +171,7 @@ __device__ __forceinline__ void bwd_rec_body(const BwdParams &p) {
   }
   // CTA = (batch group bgi: rows [b0, b0 + Bl), unit group ug: units [u0, u0 + nu));
   // batch groups never wait on each other (rows are independent)
-  const int BS = p.BS, ug = blockIdx.x % p.NUG, bgi = blockIdx.x / p.NUG;
+  const int BS = p.BS, ug = bid % p.NUG, bgi = bid / p.NUG;
   const int b0 = bgi * BS, Bl = max(0, min(BS, B - b0));
   const int u0 = ug * U, nu = max(0, min(U, H - u0));
   const int kr = KP > 1 ? (ug & 1) : 0;  // this CTA's K share (its rank in the pair)
@@ -485,10 +486,17 @@ __device__ __forceinline__ void bwd_rec_body(const BwdParams &p) {
   }
 }
 
-__global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p) { bwd_rec_body<1>(p); }
+// p's problem on the first p.per CTAs; q's (a second direction of the same
+// shape, its own pointers and counters) on the next q.per, if the grid has them
+__global__ void __launch_bounds__(NT, 1) bwd_rec_kernel(const BwdParams p, const BwdParams q) {
+  if ((int)blockIdx.x < p.per) bwd_rec_body<1>(p, (int)blockIdx.x);
+  else bwd_rec_body<1>(q, (int)blockIdx.x - p.per);
+}
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT, 1)
-    bwd_rec_pair_kernel(const BwdParams p) {
-  bwd_rec_body<2>(p);
+    bwd_rec_pair_kernel(const BwdParams p, const BwdParams q) {
+  // (p.per is even: a pair never straddles the two problems)
+  if ((int)blockIdx.x < p.per) bwd_rec_body<2>(p, (int)blockIdx.x);
+  else bwd_rec_body<2>(q, (int)blockIdx.x - p.per);
 }
 
 // out[c][r] = in[r][c] for an R x C row-major matrix (ldi, ldo: row strides),
@@ -847,33 +855,40 @@ cudaError_t launch_add(float *dst, const float *src, size_t n, cudaStream_t s) {
 
 int bwd_units_per_cta(int H, int B, int nG, int nsm) { return plan_rec(H, B, nG, nsm, false).U; }
 
-cudaError_t launch_bwd_rec(const BwdRecArgs &a, int nsm, cudaStream_t s) {
-  const int nG = a.cell == CELL_LSTM ? 4 : 3;
+static BwdParams bwd_params(const BwdRecArgs &a, const RecPlan &rp) {
+  BwdParams p{};
+  p.T = a.T; p.B = a.B; p.H = a.H; p.cell = a.cell; p.U = rp.U;
+  p.Gp = rp.Gp; p.KC = rp.KC; p.KS = rp.KS; p.BS = rp.BS; p.NUG = rp.NUG; p.NB = rp.NB;
+  p.KP = rp.KP; p.Gh = rp.Gh; p.per = rp.NBG * rp.NUG;
+  p.Whh = a.Whh; p.ldw = a.ldw;
+  p.gates = a.gates; p.zh = a.zh; p.cs = a.cs; p.c0 = a.c0; p.hp = a.hp;
+  p.dy = a.dy; p.dhn = a.dhn; p.dcn = a.dcn; p.lengths = a.lengths;
+  p.cr = a.cr; p.clo = a.clo; p.chi = a.chi;
+  p.DA = a.DA; p.DR = a.DR; p.dh0 = a.dh0; p.dc0 = a.dc0;
+  p.ctr = a.ctr; p.err = a.err; p.timeout_ns = a.timeout_ns; p.drop_arrival = a.drop_arrival;
+  p.trace = a.trace;
+  return p;
+}
+
+cudaError_t launch_bwd_rec(const BwdRecArgs &a, int nsm, cudaStream_t s, const BwdRecArgs *a2) {
+  const int nG = a.cell == CELL_LSTM ? 4 : 3, nd = a2 ? 2 : 1;
+  if (a2 && (a2->T != a.T || a2->B != a.B || a2->H != a.H || a2->cell != a.cell))
+    return cudaErrorInvalidValue;
   for (int pass = 0; pass < 2; ++pass) {
     // the K split over CTA pairs first; without it if that cluster grid
-    // cannot be co-resident
-    const RecPlan rp = plan_rec(a.H, a.B, nG, nsm, pass == 0);
+    // cannot be co-resident.  Two problems share the SMs half and half.
+    const RecPlan rp = plan_rec(a.H, a.B, nG, nsm / nd, pass == 0);
     if (rp.U < 1) return cudaErrorInvalidConfiguration;
     if (pass == 1 && rp.KP > 1) return cudaErrorInvalidConfiguration;
-    BwdParams p{};
-    p.T = a.T; p.B = a.B; p.H = a.H; p.cell = a.cell; p.U = rp.U;
-    p.Gp = rp.Gp; p.KC = rp.KC; p.KS = rp.KS; p.BS = rp.BS; p.NUG = rp.NUG; p.NB = rp.NB;
-    p.KP = rp.KP; p.Gh = rp.Gh;
-    p.Whh = a.Whh; p.ldw = a.ldw;
-    p.gates = a.gates; p.zh = a.zh; p.cs = a.cs; p.c0 = a.c0; p.hp = a.hp;
-    p.dy = a.dy; p.dhn = a.dhn; p.dcn = a.dcn; p.lengths = a.lengths;
-    p.cr = a.cr; p.clo = a.clo; p.chi = a.chi;
-    p.DA = a.DA; p.DR = a.DR; p.dh0 = a.dh0; p.dc0 = a.dc0;
-    p.ctr = a.ctr; p.err = a.err; p.timeout_ns = a.timeout_ns; p.drop_arrival = a.drop_arrival;
-    p.trace = a.trace;
+    BwdParams p = bwd_params(a, rp), q = bwd_params(a2 ? *a2 : a, rp);
+    const int grid = nd * p.per;
     const size_t smem = rp.smem;
     const void *fn = rp.KP > 1 ? (const void *)bwd_rec_pair_kernel : (const void *)bwd_rec_kernel;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    void *args[] = {&p};
-    if (rp.KP == 1)
-      return cudaLaunchCooperativeKernel(fn, dim3(rp.NBG * rp.NUG), dim3(NT), args, smem, s);
-    if (tc_launch_clustered(fn, rp.NBG * rp.NUG, NT, 2, smem, args, s, &e)) return e;
+    void *args[] = {&p, &q};
+    if (rp.KP == 1) return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(NT), args, smem, s);
+    if (tc_launch_clustered(fn, grid, NT, 2, smem, args, s, &e)) return e;
   }
   return cudaErrorInvalidConfiguration;
 }

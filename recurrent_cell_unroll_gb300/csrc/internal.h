@@ -242,7 +242,11 @@ struct BwdRecArgs {
 };
 // hidden units per CTA of the reverse-time kernel, 0 if W_hh^T does not fit
 int bwd_units_per_cta(int H, int B, int nG, int nsm);
-cudaError_t launch_bwd_rec(const BwdRecArgs &a, int nsm, cudaStream_t s);
+// a2: a second problem of the same T, B, H and cell (the other direction of a
+// bidirectional layer, with its own buffers and counters) in the same launch,
+// each on half of the SMs
+cudaError_t launch_bwd_rec(const BwdRecArgs &a, int nsm, cudaStream_t s,
+                           const BwdRecArgs *a2 = nullptr);
 cudaError_t launch_transpose(const float *in, int R, int C, int ldi, float *out, int ldo,
                              cudaStream_t s);
 // the same, rounded to bf16 (a tensor-core GEMM operand), and a row-wise
