@@ -447,8 +447,8 @@ TRAFFIC = {
     ("lstm_f32_T80_B1_512x256", "recurrent_cluster"): 1.41e6,
     ("rssm_f32_B50_T50_S20_A6_H200", "rssm_unroll"): 1.55e6,
     ("rssm_actor_f32_B50_T50_S20_A6_H200_X200", "rssm_unroll"): 1.69e6,
-    ("lstm_train_f32_T500_B64_256x512", "bwd_recurrent"): 633.5e6,
-    ("bilstm_train_f32_varlen_B64_T500_256x512", "bwd_recurrent"): 457.4e6,
+    ("lstm_train_f32_T500_B64_256x512", "bwd_recurrent"): 633.6e6,
+    ("bilstm_train_f32_varlen_B64_T500_256x512", "bwd_recurrent"): 941.7e6,
     ("rssm_train_f32_B50_T50_S20_A6_H200", "rssm_bwd_chain"): 18.7e6,
     ("gru_train_bf16_3L_T512_B256_1024", "bwd_recurrent_tc"): 6688.3e6,
 }
