@@ -141,6 +141,10 @@ BWD_BF16_SPECS = [
     wl.GRU_3L.scaled(T=5, B=24, in_dim=16, hidden=32, layers=2, bidir=True, h0_std=0.3),
     wl.GRU_3L.scaled(T=1, B=16, in_dim=16, hidden=32, layers=1, h0_std=0.5),
     wl.GRU_3L.scaled(T=5, B=20, in_dim=13, hidden=32, layers=1, h0_std=0.5),
+    # a bidirectional LSTM over variable lengths: both directions' FFMA
+    # reverse-time recurrences in one launch, the GEMMs on the tensor cores
+    wl.BILSTM_VAR.scaled(T=8, B=12, in_dim=16, hidden=32, varlen=(1, 8), dtype="bf16",
+                         h0_std=0.3, c0_std=0.3),
 ]
 
 
