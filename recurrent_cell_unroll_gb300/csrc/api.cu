@@ -1256,6 +1256,10 @@ extern "C" int rnn_backward(rcu_rnn_t h, int T, int B, const float *x, const int
   float *CR = (cell == RCU_LSTM && h->cclip) ? wsf + o_cr : nullptr;
   float *BS = wsf + o_bs, *HPT = wsf + o_hpt, *DYT = wsf + o_dyt, *WSK = wsf + o_wsk;
   unsigned *ctr = (unsigned *)(wsf + o_ctl);
+  // the pieces that live from a direction's recompute to its reverse-time
+  // recurrence, by slot: 0 (every layer's first direction, and every
+  // direction run on its own) and 1 (a bidirectional layer's second direction
+  // when both recurrences share one launch); run_dir picks them by slot
   float *const zin_0 = zin, *const zh_0 = zh, *const cs_0 = cs, *const DA_0 = DA, *const DR_0 = DR,
               *const hp_0 = hp, *const DYM_0 = DYM, *const CR_0 = CR;
   unsigned *const ctr_0 = ctr;
